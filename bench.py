@@ -1,0 +1,469 @@
+#!/usr/bin/env python
+"""Benchmark of the chunkwise gated delta rule on one GB300 (or N replicas).
+
+One step = the forward pass and the complete backward pass (recompute policy)
+of the KDA workload B=2, T=8192, H=32, dk=dv=128, bf16 I/O, per-channel gate
+(the configuration the tokens/s headline is quoted on), synthetic seeded
+inputs resident in HBM. Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun every rank runs its own replica (weak scaling, no data-path
+collective); the elapsed time is the max over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "KDA fwd+bwd tokens/s and TFLOP/s (% bf16 tensor peak), 1xGB300"
+BT = 64
+WORKLOAD_IDX = 4
+
+
+# ---------------------------------------------------------------- FLOP model
+def chunk_lengths(case):
+    out = []
+    ss = case.seq_starts
+    for n in range(case.N):
+        L = ss[n + 1] - ss[n]
+        out += [min(BT, L - a) for a in range(0, L, BT)]
+    return out
+
+
+def flops_model(case):
+    """Algorithmic dense FLOPs (2 per multiply-add) per step, summed over
+    chunk x head with the exact chunk length n and d = dk = dv:
+    forward 10 n^2 d + 6 n d^2 + 2 n^3/3, backward 16 n^2 d + 12 n d^2,
+    recompute 8 n^2 d + 4 n d^2 + 2 n^3/3."""
+    d = case.K
+    fwd = bwd = rec = 0.0
+    for n in chunk_lengths(case):
+        fwd += 10 * n * n * d + 6 * n * d * d + 2 * n ** 3 / 3
+        bwd += 16 * n * n * d + 12 * n * d * d
+        rec += 8 * n * n * d + 4 * n * d * d + 2 * n ** 3 / 3
+    return fwd * case.H, bwd * case.H, rec * case.H
+
+
+def kernel_work(case):
+    """Algorithmic FLOPs per launch of each library kernel (same model, split
+    by the products each kernel owns)."""
+    d = case.K
+    w = {}
+    acc = dict(k_prep=0.0, k_fwd_scan=0.0, k_fwd_scan_recompute=0.0, k_bwd_scan=0.0,
+               k_bwd_dstate=0.0, k_bwd_intra=0.0)
+    for n in chunk_lengths(case):
+        acc["k_prep"] += 8 * n * n * d + 2 * n ** 3 / 3
+        acc["k_fwd_scan"] += 6 * n * d * d + 2 * n * n * d
+        acc["k_fwd_scan_recompute"] += 4 * n * d * d
+        acc["k_bwd_scan"] += 6 * n * d * d + 4 * n * n * d
+        acc["k_bwd_dstate"] += 4 * n * n * d + 6 * n * d * d
+        acc["k_bwd_intra"] += 8 * n * n * d
+    for k, v in acc.items():
+        w[k] = v * case.H
+    return w
+
+
+def token_bytes(case):
+    """Algorithmic HBM bytes of one fwd+bwd step: every input read and every
+    output written once (fwd: q,k,v,beta,g,h0 in, o,ht out; bwd: q,k,v,beta,g,
+    h0,do,dht in, dq,dk,dv,dbeta,dg,dh0 out)."""
+    e = 2 if case.io == "bf16" else 4
+    T = case.B * case.T
+    H, K, V = case.H, case.K, case.V
+    gb = {"channel": 4 * K, "scalar": 4, "none": 0}[case.gate]
+    st = 4 * K * V * case.N * H
+    fwd = T * H * (e * (2 * K + V) + e + gb + e * V) + st * (2 if case.h0 is not None else 1)
+    bwd = T * H * (e * (2 * K + 2 * V) + e + gb + e * (2 * K + V) + e + gb) + st * 3
+    return fwd + bwd
+
+
+# ------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, dev_uuid=None):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", "clocks.csv")
+        self.uuid = dev_uuid
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                   "-lms", "200"]
+            if self.uuid:
+                cmd += ["--id=" + self.uuid]
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(cmd, stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ helpers
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sus=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    sm_max=float(d.get("sm_max_mhz", 2070.0)), source="measured")
+    except Exception:
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, sm_max=2070.0, source="fallback")
+
+
+def traffic_for(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, only while the
+    kernel's source file is unchanged since the capture (else None)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    srcdir = os.path.join(ROOT, "chunkwise_delta_rule_gb300", "csrc")
+    for line in open(path):
+        if line.startswith("#") or not line.strip():
+            continue
+        parts = line.split()
+        if len(parts) < 4 or parts[0] != kernel:
+            continue
+        fname, digest, nbytes = parts[1], parts[2], parts[3]
+        try:
+            cur = hashlib.sha256(open(os.path.join(srcdir, fname), "rb").read()).hexdigest()[:16]
+        except OSError:
+            return None
+        if cur == digest:
+            return float(nbytes)
+    return None
+
+
+class KernelTime(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 40), ("launches", ctypes.c_int), ("total_ms", ctypes.c_double)]
+
+
+def profile_begin(lib):
+    lib.kda_profile_begin.restype = ctypes.c_int
+    lib.kda_profile_begin()
+
+
+def profile_end(lib):
+    arr = (KernelTime * 32)()
+    lib.kda_profile_end.argtypes = [ctypes.POINTER(KernelTime), ctypes.c_int]
+    lib.kda_profile_end.restype = ctypes.c_int
+    n = lib.kda_profile_end(arr, 32)
+    return {arr[i].name.decode(): (arr[i].launches, arr[i].total_ms) for i in range(max(n, 0))}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ----------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+
+    import chunkwise_delta_rule_gb300 as kda
+    from chunkwise_delta_rule_gb300 import _lib
+    from workloads import CONFIGS, make_config_case
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+    cfg = CONFIGS[args.config]
+    case_cpu = make_config_case(args.config)
+    case = case_cpu.to(dev)
+    lib = _lib.load()
+    p = kda.make_problem(case.q, case.k, case.v, case.g, case.beta, gate=case.gate,
+                         scale=case.scale, initial_state=case.h0, cu_seqlens=case.cu_seqlens)
+    wf = torch.empty(kda.kda_workspace_size(p, False), dtype=torch.uint8, device=dev)
+    wb = torch.empty(kda.kda_workspace_size(p, True), dtype=torch.uint8, device=dev)
+    l2 = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step():
+        kda.kda_chunk_fwd(p, workspace=wf)
+        kda.kda_chunk_bwd(p, case.do, case.dht, workspace=wb)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    def barrier():
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        if uuid and not uuid.startswith("GPU-"):
+            uuid = "GPU-" + uuid
+    except Exception:
+        uuid = None
+    clocks = ClockSampler(uuid) if rank == 0 else None
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    barrier()
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    profile_begin(lib)
+    t_wall = time.perf_counter()
+    for i in range(K):
+        l2.zero_()                                  # flush L2 between timed steps
+        ev[i][0].record()
+        kda.kda_chunk_fwd(p, workspace=wf)
+        ev[i][1].record()
+        kda.kda_chunk_bwd(p, case.do, case.dht, workspace=wb)
+        ev[i][2].record()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    barrier()
+    kern = profile_end(lib)
+    clk = clocks.stop() if clocks else None
+    fwd_ms = [a.elapsed_time(b) for a, b, _ in ev]
+    bwd_ms = [b.elapsed_time(c) for _, b, c in ev]
+    step_ms = sum(fwd_ms) / K + sum(bwd_ms) / K
+    if ws > 1:
+        import torch.distributed as dist
+        t = torch.tensor([step_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms = float(t.item())
+
+    tokens = case.B * case.T
+    fl_f, fl_b, fl_r = flops_model(case)
+    value = ws * tokens / (step_ms * 1e-3)
+    tflops = ws * (fl_f + fl_b) / (step_ms * 1e-3) / 1e12
+    tflops_exec = ws * (fl_f + fl_b + fl_r) / (step_ms * 1e-3) / 1e12
+    pk = peaks()
+    launches = sum(v[0] for v in kern.values())
+    # dominant kernel and its roofline
+    work = kernel_work(case)
+    dom = max(kern.items(), key=lambda kv: kv[1][1])[0] if kern else None
+    roof = None
+    if dom:
+        n_l, tot = kern[dom]
+        avg_ms = tot / n_l
+        fl = work.get(dom, 0.0)
+        sm_mhz = clk["sm_mhz"] if clk else pk["sm_max"]
+        alu_peak = 152 * 128 * 2 * pk["sm_max"] * 1e6 / 1e12   # FP32 FMA lanes x 2 x clock
+        achieved = fl / (avg_ms * 1e-3) / 1e12
+        roof = {"kernel": dom, "bound": "alu", "achieved": round(achieved, 3),
+                "peak": round(alu_peak, 1), "unit": "TFLOP/s", "frac": round(achieved / alu_peak, 4),
+                "traffic": traffic_for(dom), "avg_launch_ms": round(avg_ms, 4),
+                "note": "fp32 CUDA-core FMA kernel; peak = 152 SMs x 128 FP32 lanes x 2 x max SM clock",
+                "sm_mhz_under_load": sm_mhz}
+    kernels = {k: {"launches": v[0], "avg_ms": round(v[1] / v[0], 4),
+                   "share": round(v[1] / max(sum(x[1] for x in kern.values()), 1e-9), 4)}
+               for k, v in kern.items()}
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, case_cpu, dev, kda, K)
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu:
+        cpu = cpu_baseline(case_cpu)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws,
+            "steps": K, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if cfg["io"] == "bf16" else "fp32",
+            "data": "synthetic (seeded; shapes and distributions of the workload)",
+            "config": {"workload": cfg["name"], "B": case.B, "T": case.T, "H": case.H, "dk": case.K,
+                       "dv": case.V, "gate": case.gate, "io": cfg["io"], "chunk": BT,
+                       "policy": "recompute", "parallelism": f"replicas x{ws}",
+                       "l2": "flushed by a 256 MiB write before every timed step"},
+            "tflops": round(tflops, 2), "tflops_executed": round(tflops_exec, 2),
+            "frac_bf16_peak": round(tflops / pk["bf16"], 4),
+            "frac_bf16_peak_sustained": round(tflops / pk["bf16_sus"], 4),
+            "hbm_algorithmic_gbs": round(ws * token_bytes(case) / (step_ms * 1e-3) / 1e9, 1),
+            "peaks_source": pk["source"],
+            "fwd_ms": round(sum(fwd_ms) / K, 4), "bwd_ms": round(sum(bwd_ms) / K, 4),
+            "roofline": roof, "kernels": kernels, "gpu_launches": launches,
+            "clocks": clk, "e2e": e2e, "cpu_baseline": cpu, "wall_s": round(t_wall, 3),
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_e2e(args, case_cpu, dev, kda, K):
+    """Same metric through the public API with host buffers: every step copies
+    the inputs from pinned host memory, runs forward and backward, and reads
+    every output back to pinned host memory."""
+    import torch
+    names = ["q", "k", "v", "g", "beta", "h0", "do", "dht"]
+    host = {n: getattr(case_cpu, n).pin_memory() for n in names if getattr(case_cpu, n) is not None}
+    devt = {n: torch.empty_like(t, device=dev) for n, t in host.items()}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    outs_host = None
+    d2h = 0
+    s0 = torch.cuda.Event(enable_timing=True)
+    s1 = torch.cuda.Event(enable_timing=True)
+
+    def one():
+        nonlocal outs_host, d2h
+        for n, t in host.items():
+            devt[n].copy_(t, non_blocking=True)
+        p = kda.make_problem(devt["q"], devt["k"], devt["v"], devt.get("g"), devt["beta"],
+                             gate=case_cpu.gate, scale=case_cpu.scale, initial_state=devt.get("h0"))
+        o, ht, _ = kda.kda_chunk_fwd(p)
+        grads = kda.kda_chunk_bwd(p, devt["do"], devt.get("dht"))
+        res = [o, ht] + [x for x in grads if x is not None]
+        if outs_host is None:
+            outs_host = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in res]
+            d2h = sum(x.numel() * x.element_size() for x in res)
+        for hbuf, x in zip(outs_host, res):
+            hbuf.copy_(x, non_blocking=True)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize()
+    s0.record()
+    for _ in range(K):
+        one()
+    s1.record()
+    torch.cuda.synchronize()
+    ms = s0.elapsed_time(s1) / K
+    tokens = case_cpu.B * case_cpu.T
+    return {"value": round(tokens / (ms * 1e-3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+# ------------------------------------------------------ oracle (CPU) timing
+def oracle_sample(case_cpu, pairs_wanted=None):
+    """A bounded sample of the workload for the CPU oracle: whole (sequence,
+    head) pairs, one per host core by default."""
+    cores = os.cpu_count() or 1
+    npairs = pairs_wanted or min(case_cpu.N * case_cpu.H, max(cores, 1))
+    pairs = [(i % case_cpu.N, (i * 7) % case_cpu.H) for i in range(npairs)]
+    seen = []
+    for p in pairs:
+        if p not in seen:
+            seen.append(p)
+    return seen, cores
+
+
+def time_oracle(case_cpu, pairs, cores):
+    from oracle.cases import pairs_arrays, run_pairs_arrays
+    cat, starts = pairs_arrays(case_cpu, pairs)
+    t = time.perf_counter()
+    run_pairs_arrays(case_cpu, cat, starts, backward=True, nthreads=cores)
+    dt = time.perf_counter() - t
+    ss = case_cpu.seq_starts
+    tok_heads = sum(ss[n + 1] - ss[n] for n, _ in pairs)
+    return tok_heads / case_cpu.H / dt, dt, tok_heads
+
+
+def cpu_baseline(case_cpu):
+    pairs, cores = oracle_sample(case_cpu)
+    v, dt, th = time_oracle(case_cpu, pairs, cores)
+    return {"value": round(v, 2), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{len(pairs)} whole (sequence, head) pairs = {th} token-heads, fp64 "
+                      f"recurrence + BPTT, {dt:.1f} s wall; tokens/s = token-heads / H / wall"}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from workloads import CONFIGS, make_config_case
+    cfg = CONFIGS[args.config]
+    case_cpu = make_config_case(args.config)
+    pairs, cores = oracle_sample(case_cpu, pairs_wanted=max(1, min(os.cpu_count() or 1, 8)))
+    for _ in range(args.warmup):
+        time_oracle(case_cpu, pairs[:1], 1)
+    vals, dts, th = [], [], 0
+    for _ in range(args.steps):
+        v, dt, th = time_oracle(case_cpu, pairs, cores)
+        vals.append(v)
+        dts.append(dt)
+    value = statistics.median(vals)
+    sample = (f"{len(pairs)} whole (sequence, head) pairs per step = {th} token-heads of the "
+              f"workload, fp64 recurrence + BPTT on {cores} host threads")
+    line = {"metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * case_cpu.B * case_cpu.T / value, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded; shapes and distributions of the workload)",
+            "config": {"workload": cfg["name"], "B": case_cpu.B, "T": case_cpu.T, "H": case_cpu.H,
+                       "dk": case_cpu.K, "dv": case_cpu.V, "gate": case_cpu.gate, "io": cfg["io"]},
+            "impl": "reference",
+            "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=WORKLOAD_IDX)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,372 @@
+// C ABI of libkda.so: argument validation, workspace layout, launch order.
+// Declarations and the contract of every entry point are in include/kda.h.
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/kda.h"
+#include "kda_internal.cuh"
+
+namespace {
+
+thread_local std::string g_err;
+
+kda_status fail(kda_status st, const std::string& msg) {
+    g_err = msg;
+    return st;
+}
+
+constexpr size_t ALIGN = 256;
+size_t up(size_t x) { return (x + ALIGN - 1) / ALIGN * ALIGN; }
+
+struct Dims {
+    int N = 0, NC = 0, Ttot = 0, D = 0, H = 0;
+};
+
+// Checks the size fields; fills d. Returns KDA_OK or an error (message set).
+kda_status check_dims(const kda_problem* p, Dims& d) {
+    if (!p) return fail(KDA_ERR_INVALID_ARG, "problem is NULL");
+    if (p->B < 1 || p->T < 0 || p->H < 1 || p->K < 1 || p->V < 1)
+        return fail(KDA_ERR_INVALID_ARG, "B, H, K, V must be >= 1 and T >= 0");
+    if (p->K != p->V) return fail(KDA_ERR_UNSUPPORTED, "K != V is not built");
+    if (p->K != 64 && p->K != 128) return fail(KDA_ERR_UNSUPPORTED, "K must be 64 or 128");
+    if (p->H > 65535) return fail(KDA_ERR_UNSUPPORTED, "H > 65535");
+    if (p->io != KDA_BF16 && p->io != KDA_FP32) return fail(KDA_ERR_INVALID_ARG, "unknown io dtype");
+    if (p->gate != KDA_GATE_NONE && p->gate != KDA_GATE_SCALAR && p->gate != KDA_GATE_CHANNEL)
+        return fail(KDA_ERR_INVALID_ARG, "unknown gate kind");
+    if (p->save_policy != 0 && p->save_policy != 1)
+        return fail(KDA_ERR_INVALID_ARG, "save_policy must be 0 or 1");
+    const long long tok = (long long)p->B * p->T;
+    if (tok > 0x7fffffffLL / 2) return fail(KDA_ERR_UNSUPPORTED, "too many tokens");
+    d.Ttot = (int)tok;
+    d.D = p->K;
+    d.H = p->H;
+    const long long per = (p->T + kda::BT - 1) / kda::BT;
+    if (p->cu_seqlens) {
+        if (p->B != 1) return fail(KDA_ERR_INVALID_ARG, "packed sequences need B == 1");
+        if (p->N < 1) return fail(KDA_ERR_INVALID_ARG, "packed sequences need N >= 1");
+        d.N = p->N;
+        const long long nc = per + p->N;
+        if (nc > 0x7fffffffLL) return fail(KDA_ERR_UNSUPPORTED, "too many chunks");
+        d.NC = (int)nc;
+    } else {
+        d.N = p->B;
+        d.NC = (int)(per * p->B);
+    }
+    return KDA_OK;
+}
+
+struct Layout {
+    size_t table = 0, fcore = 0, fextra = 0, bwd = 0;
+};
+
+Layout layout(const Dims& d) {
+    Layout L;
+    const size_t NC = (size_t)d.NC, H = (size_t)d.H, D = (size_t)d.D, BT = kda::BT;
+    const size_t N = (size_t)d.N;
+    L.table = up(sizeof(int32_t) * NC) * 2 + up(sizeof(int32_t) * (N + 1)) + up(sizeof(int32_t) * N) * 2 +
+              up(sizeof(int32_t));
+    const size_t chd = NC * H;
+    L.fcore = up(4 * chd * BT * D) * 4 + up(4 * chd * BT * BT) * 2 + up(4 * chd * D);
+    L.fextra = up(4 * chd * BT * D) + up(4 * chd * D * D);
+    L.bwd = up(4 * chd * BT * D) * 4 + up(4 * chd * D * D) + up(4 * chd * BT * BT) * 2 +
+            up(4 * chd * D) + up(4 * chd * BT);
+    return L;
+}
+
+struct Carver {
+    char* p;
+    template <class T>
+    T* take(size_t bytes) {
+        T* r = reinterpret_cast<T*>(p);
+        p += up(bytes);
+        return r;
+    }
+};
+
+kda::Table carve_table(Carver& c, const Dims& d) {
+    kda::Table t;
+    t.chunk_tok0 = c.take<int32_t>(sizeof(int32_t) * d.NC);
+    t.chunk_len = c.take<int32_t>(sizeof(int32_t) * d.NC);
+    t.seq_chunk0 = c.take<int32_t>(sizeof(int32_t) * (d.N + 1));
+    t.seq_tok0 = c.take<int32_t>(sizeof(int32_t) * d.N);
+    t.seq_len = c.take<int32_t>(sizeof(int32_t) * d.N);
+    t.err = c.take<int32_t>(sizeof(int32_t));
+    return t;
+}
+
+void carve_fwd(Carver& c, const Dims& d, kda::Fwd& f, bool extra) {
+    const size_t chd = (size_t)d.NC * d.H, D = d.D, BT = kda::BT;
+    f.W = c.take<float>(4 * chd * BT * D);
+    f.U = c.take<float>(4 * chd * BT * D);
+    f.KG = c.take<float>(4 * chd * BT * D);
+    f.QG = c.take<float>(4 * chd * BT * D);
+    f.AQK = c.take<float>(4 * chd * BT * BT);
+    f.AINV = c.take<float>(4 * chd * BT * BT);
+    f.GL = c.take<float>(4 * chd * D);
+    if (extra) {
+        f.R = c.take<float>(4 * chd * BT * D);
+        f.SIN = c.take<float>(4 * chd * D * D);
+    } else {
+        f.R = nullptr;
+        f.SIN = nullptr;
+    }
+}
+
+void carve_bwd(Carver& c, const Dims& d, kda::Bwd& b) {
+    const size_t chd = (size_t)d.NC * d.H, D = d.D, BT = kda::BT;
+    b.P = c.take<float>(4 * chd * BT * D);
+    b.QS = c.take<float>(4 * chd * BT * D);
+    b.PS = c.take<float>(4 * chd * BT * D);
+    b.FB = c.take<float>(4 * chd * BT * D);
+    b.SBP = c.take<float>(4 * chd * D * D);
+    b.DM = c.take<float>(4 * chd * BT * BT);
+    b.HQ = c.take<float>(4 * chd * BT * BT);
+    b.LAMB = c.take<float>(4 * chd * D);
+    b.DBW = c.take<float>(4 * chd * BT);
+}
+
+kda::Shape shape_of(const kda_problem* p, const Dims& d) {
+    kda::Shape s;
+    s.H = p->H;
+    s.K = p->K;
+    s.V = p->V;
+    s.N = d.N;
+    s.NC = d.NC;
+    s.Ttot = d.Ttot;
+    s.scale = p->scale > 0.f ? p->scale : 1.0f / sqrtf((float)p->K);
+    return s;
+}
+
+kda_status check_inputs(const kda_problem* p, const Dims& d) {
+    if (d.Ttot > 0 && (!p->q || !p->k || !p->v || !p->beta))
+        return fail(KDA_ERR_INVALID_ARG, "q, k, v and beta must be non-NULL");
+    if (p->gate == KDA_GATE_NONE && p->g) return fail(KDA_ERR_INVALID_ARG, "g must be NULL without a gate");
+    if (p->gate != KDA_GATE_NONE && !p->g && d.Ttot > 0)
+        return fail(KDA_ERR_INVALID_ARG, "g must be non-NULL with a gate");
+    return KDA_OK;
+}
+
+kda_status check_ws(void* ws, size_t ws_bytes, size_t need) {
+    if (need == 0) return KDA_OK;
+    if (!ws) return fail(KDA_ERR_WORKSPACE, "workspace is NULL");
+    if (reinterpret_cast<uintptr_t>(ws) % ALIGN) return fail(KDA_ERR_WORKSPACE, "workspace not 256-byte aligned");
+    if (ws_bytes < need)
+        return fail(KDA_ERR_WORKSPACE, "workspace too small: need " + std::to_string(need) + " bytes");
+    return KDA_OK;
+}
+
+kda_status cuda_fail(cudaError_t e, const char* where) {
+    return fail(KDA_ERR_CUDA, std::string(where) + ": " + cudaGetErrorString(e));
+}
+
+size_t state_bytes(const Dims& d) { return sizeof(float) * (size_t)d.N * d.H * d.D * d.D; }
+
+// ------------------------------------------------------------------ tracing
+struct Prof {
+    bool on = false;
+    struct Rec {
+        const char* name;
+        cudaEvent_t a, b;
+    };
+    std::vector<Rec> recs;
+    std::vector<cudaEvent_t> pool;
+    size_t used = 0;
+    cudaEvent_t ev() {
+        if (used == pool.size()) {
+            cudaEvent_t e;
+            if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+            pool.push_back(e);
+        }
+        return pool[used++];
+    }
+};
+Prof g_prof;
+
+// Runs one launch, bracketed by events when tracing is on.
+template <class F>
+cudaError_t traced(const char* name, cudaStream_t cs, F&& launch) {
+    if (!g_prof.on) return launch();
+    cudaEvent_t a = g_prof.ev(), b = g_prof.ev();
+    if (a) cudaEventRecord(a, cs);
+    cudaError_t e = launch();
+    if (b) cudaEventRecord(b, cs);
+    if (a && b) g_prof.recs.push_back({name, a, b});
+    return e;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kda_abi_version(void) { return 1; }
+
+const char* kda_last_error(void) { return g_err.c_str(); }
+
+size_t kda_workspace_size(const kda_problem* p, int for_backward) {
+    Dims d;
+    if (check_dims(p, d) != KDA_OK) return 0;
+    if (d.Ttot == 0) return 0;
+    const Layout L = layout(d);
+    if (!for_backward) return L.table + (p->save_policy ? 0 : L.fcore);
+    return L.table + (p->save_policy ? 0 : L.fcore + L.fextra) + L.bwd;
+}
+
+size_t kda_saved_size(const kda_problem* p) {
+    Dims d;
+    if (check_dims(p, d) != KDA_OK) return 0;
+    if (!p->save_policy || d.Ttot == 0) return 0;
+    const Layout L = layout(d);
+    return L.fcore + L.fextra;
+}
+
+kda_status kda_chunk_fwd(const kda_problem* p, void* o, float* ht, void* saved, void* ws,
+                         size_t ws_bytes, kda_stream_t stream) {
+    Dims d;
+    kda_status st = check_dims(p, d);
+    if (st != KDA_OK) return st;
+    if ((st = check_inputs(p, d)) != KDA_OK) return st;
+    if (d.Ttot > 0 && !o) return fail(KDA_ERR_INVALID_ARG, "o must be non-NULL");
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    if (d.Ttot == 0) {  // no tokens: the final state is the initial state
+        if (ht) {
+            cudaError_t e = p->h0 ? cudaMemcpyAsync(ht, p->h0, state_bytes(d), cudaMemcpyDeviceToDevice, cs)
+                                  : cudaMemsetAsync(ht, 0, state_bytes(d), cs);
+            if (e != cudaSuccess) return cuda_fail(e, "copy h0");
+        }
+        return KDA_OK;
+    }
+    if ((st = check_ws(ws, ws_bytes, kda_workspace_size(p, 0))) != KDA_OK) return st;
+    if (p->save_policy && (st = check_ws(saved, kda_saved_size(p), kda_saved_size(p))) != KDA_OK)
+        return fail(KDA_ERR_WORKSPACE, "saved buffer: " + g_err);
+    const kda::Shape s = shape_of(p, d);
+    Carver cw{static_cast<char*>(ws)};
+    kda::Table t = carve_table(cw, d);
+    kda::Fwd f;
+    if (p->save_policy) {
+        Carver cs2{static_cast<char*>(saved)};
+        carve_fwd(cs2, d, f, true);
+    } else {
+        carve_fwd(cw, d, f, false);
+    }
+    const int bf16 = p->io == KDA_BF16;
+    cudaError_t e = traced("k_table", cs, [&] { return kda::launch_table(s, p->B, p->T, p->cu_seqlens, t, cs); });
+    if (e != cudaSuccess) return cuda_fail(e, "chunk table");
+    e = traced("k_prep", cs, [&] { return kda::launch_prep(s, bf16, (int)p->gate, p->q, p->k, p->v, p->beta, p->g, t, f, cs); });
+    if (e != cudaSuccess) return cuda_fail(e, "prep");
+    e = traced("k_fwd_scan", cs, [&] { return kda::launch_fwd_scan(s, bf16, p->save_policy ? 3 : 1, p->h0, t, f, o, ht, cs); });
+    if (e != cudaSuccess) return cuda_fail(e, "forward scan");
+    return KDA_OK;
+}
+
+kda_status kda_chunk_bwd(const kda_problem* p, const void* dout, const float* dht, const void* saved,
+                         void* dq, void* dk, void* dv, float* dg, void* dbeta, float* dh0, void* ws,
+                         size_t ws_bytes, kda_stream_t stream) {
+    Dims d;
+    kda_status st = check_dims(p, d);
+    if (st != KDA_OK) return st;
+    if ((st = check_inputs(p, d)) != KDA_OK) return st;
+    if (d.Ttot > 0 && (!dout || !dq || !dk || !dv || !dbeta))
+        return fail(KDA_ERR_INVALID_ARG, "dout, dq, dk, dv and dbeta must be non-NULL");
+    if (p->gate == KDA_GATE_NONE && dg) return fail(KDA_ERR_INVALID_ARG, "dg must be NULL without a gate");
+    if (p->gate != KDA_GATE_NONE && !dg && d.Ttot > 0)
+        return fail(KDA_ERR_INVALID_ARG, "dg must be non-NULL with a gate");
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    if (d.Ttot == 0) {  // no tokens: dh0 = dht
+        if (dh0) {
+            cudaError_t e = dht ? cudaMemcpyAsync(dh0, dht, state_bytes(d), cudaMemcpyDeviceToDevice, cs)
+                                : cudaMemsetAsync(dh0, 0, state_bytes(d), cs);
+            if (e != cudaSuccess) return cuda_fail(e, "copy dht");
+        }
+        return KDA_OK;
+    }
+    if ((st = check_ws(ws, ws_bytes, kda_workspace_size(p, 1))) != KDA_OK) return st;
+    if (p->save_policy) {
+        if (!saved) return fail(KDA_ERR_WORKSPACE, "policy A needs the saved buffer");
+        if (reinterpret_cast<uintptr_t>(saved) % ALIGN)
+            return fail(KDA_ERR_WORKSPACE, "saved buffer not 256-byte aligned");
+    }
+    const kda::Shape s = shape_of(p, d);
+    Carver cw{static_cast<char*>(ws)};
+    kda::Table t = carve_table(cw, d);
+    kda::Fwd f;
+    if (p->save_policy) {
+        Carver cs2{static_cast<char*>(const_cast<void*>(saved))};
+        carve_fwd(cs2, d, f, true);
+    } else {
+        carve_fwd(cw, d, f, true);
+    }
+    kda::Bwd b;
+    carve_bwd(cw, d, b);
+    const int bf16 = p->io == KDA_BF16;
+    cudaError_t e = traced("k_table", cs, [&] { return kda::launch_table(s, p->B, p->T, p->cu_seqlens, t, cs); });
+    if (e != cudaSuccess) return cuda_fail(e, "chunk table");
+    if (!p->save_policy) {
+        e = traced("k_prep", cs, [&] { return kda::launch_prep(s, bf16, (int)p->gate, p->q, p->k, p->v, p->beta, p->g, t, f, cs); });
+        if (e != cudaSuccess) return cuda_fail(e, "prep (recompute)");
+        e = traced("k_fwd_scan_recompute", cs, [&] { return kda::launch_fwd_scan(s, bf16, 2, p->h0, t, f, nullptr, nullptr, cs); });
+        if (e != cudaSuccess) return cuda_fail(e, "forward scan (recompute)");
+    }
+    e = traced("k_bwd_scan", cs, [&] { return kda::launch_bwd_scan(s, bf16, dout, dht, t, f, b, dh0, cs); });
+    if (e != cudaSuccess) return cuda_fail(e, "reverse scan");
+    e = traced("k_bwd_dstate", cs, [&] { return kda::launch_bwd_dstate(s, bf16, dout, p->v, p->beta, t, f, b, dv, cs); });
+    if (e != cudaSuccess) return cuda_fail(e, "state-gradient consumer");
+    e = traced("k_bwd_intra", cs, [&] { return kda::launch_bwd_intra(s, bf16, (int)p->gate, p->q, p->k, p->beta, p->g, t, f, b, dq, dk, dbeta, dg, cs); });
+    if (e != cudaSuccess) return cuda_fail(e, "intra consumer");
+    return KDA_OK;
+}
+
+int kda_profile_begin(void) {
+    g_prof.on = true;
+    g_prof.recs.clear();
+    g_prof.used = 0;
+    return 0;
+}
+
+int kda_profile_end(kda_kernel_time* out, int max_entries) {
+    g_prof.on = false;
+    std::vector<kda_kernel_time> agg;
+    for (auto& r : g_prof.recs) {
+        if (cudaEventSynchronize(r.b) != cudaSuccess) return -1;
+        float ms = 0.f;
+        if (cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess) return -1;
+        size_t i = 0;
+        for (; i < agg.size(); ++i)
+            if (std::strncmp(agg[i].name, r.name, sizeof(agg[i].name)) == 0) break;
+        if (i == agg.size()) {
+            kda_kernel_time k;
+            std::memset(&k, 0, sizeof(k));
+            std::strncpy(k.name, r.name, sizeof(k.name) - 1);
+            agg.push_back(k);
+        }
+        agg[i].launches += 1;
+        agg[i].total_ms += ms;
+    }
+    g_prof.recs.clear();
+    g_prof.used = 0;
+    const int n = (int)agg.size() < max_entries ? (int)agg.size() : max_entries;
+    for (int i = 0; i < n && out; ++i) out[i] = agg[i];
+    return n;
+}
+
+kda_status kda_device_status(const kda_problem* p, const void* ws, size_t ws_bytes, kda_stream_t stream,
+                             int32_t* word) {
+    Dims d;
+    kda_status st = check_dims(p, d);
+    if (st != KDA_OK) return st;
+    if (!word) return fail(KDA_ERR_INVALID_ARG, "word is NULL");
+    *word = 0;
+    if (d.Ttot == 0) return KDA_OK;
+    const Layout L = layout(d);
+    if (!ws || ws_bytes < L.table) return fail(KDA_ERR_WORKSPACE, "workspace too small");
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(cs);
+    if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+    const size_t off = L.table - up(sizeof(int32_t));
+    e = cudaMemcpy(word, static_cast<const char*>(ws) + off, sizeof(int32_t), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "read error word");
+    if (*word) return fail(KDA_ERR_INVALID_ARG, "cu_seqlens was inconsistent and was clamped");
+    return KDA_OK;
+}
+
+}  // extern "C"

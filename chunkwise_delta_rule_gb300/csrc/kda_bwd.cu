@@ -1,0 +1,519 @@
+// Chunk-parallel backward consumers, one CTA per (chunk slot, head).
+//
+// k_bwd_dstate (a9 + a10, the contractions over the value width):
+//     dv = beta P ; <v_i, P_i> ; D = -L_<(P R^T) ; H_q = L_<=(dO R^T) ;
+//     dO S^T ; -P S^T ; F_bar = R S+bar^T ; rowsum(S .* S+bar)
+// ("ReWY" paper, Algorithm 1 steps 2-3 and "Output, state, and
+// effective-input gradients").
+//
+// k_bwd_intra (a11 / a11' + a12, the interaction contractions and chain rule):
+//     gamma*Q_g_bar = gamma*(dO S^T) + gamma*(H_q Y)
+//     gamma*E_bar   = gamma*(-P S^T) + gamma*(D Y)
+//     Y_bar/gamma   = (D^T E + H_q^T Q_g)/gamma + F_bar*lambda/gamma
+// with the pairwise decays factored as alpha = exp(G - c), zeta = exp(c - G)
+// around the per-feature midpoint c of the chunk ("Matrix intra for
+// vector-gated interactions", centered factors); chunks whose gate range
+// exceeds the threshold use 16-token sub-chunks anchored so every factor is
+// bounded; scalar gates fold exp(G_i - G_j) into D and H_q exactly and never
+// form the key Gram matrix ("Gram elimination for scalar-gate gradients").
+// Then dq = scale*gamma*Q_g_bar ; dk = beta*gamma*E_bar + Y_bar/gamma ;
+// dbeta = <k_i, gamma*E_bar_i> + <v_i, P_i> (undivided, valid at beta = 0) ;
+// G_bar = Q_g .* Q_g_bar + E .* E_bar - Y .* Y_bar plus the two state
+// endpoints at the last valid token, and dg = reverse in-chunk cumsum of
+// G_bar ("Complete Reverse Execution and Boundaries", steps 3-4).
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int SL = 32;  // value columns of S per slice in k_bwd_dstate
+
+template <typename TI, int D>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    k_bwd_dstate(Shape s, const TI* __restrict__ dout, const TI* __restrict__ v,
+                 const TI* __restrict__ beta, Table t, Fwd f, Bwd b, TI* __restrict__ dv) {
+    constexpr int LD = D + 1, LS = SL + 1;
+    extern __shared__ float smem[];
+    float* sO = smem;              // [BT][LD] dO
+    float* sP = sO + BT * LD;      // [BT][LD] P
+    float* sR = sP + BT * LD;      // [BT][LD] R
+    float* sS = sR + BT * LD;      // [D][LS] slice of S
+    float* sT = sS + D * LS;       // [D][LS] slice of S+bar
+
+    const int c = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+    const int len = t.chunk_len[c];
+    if (len <= 0) return;
+    const int tok0 = t.chunk_tok0[c];
+    const int H = s.H;
+    const size_t ch = (size_t)c * H + h;
+    const int lane = tid & 31, warp = tid >> 5;
+
+    const float* P = b.P + ch * BT * D;
+    const float* R = f.R + ch * BT * D;
+    for (int idx = tid; idx < BT * D; idx += NTHREADS) {
+        const int r = idx / D, col = idx % D;
+        sO[r * LD + col] = (r < len) ? ld(dout + ((size_t)(tok0 + r) * H + h) * D + col) : 0.f;
+        sP[r * LD + col] = P[idx];
+        sR[r * LD + col] = R[idx];
+    }
+    __syncthreads();
+    // dv = beta P and <v_i, P_i>, one warp per row
+    for (int r = warp; r < BT; r += NTHREADS / 32) {
+        float acc = 0.f;
+        if (r < len) {
+            const size_t tok = (size_t)(tok0 + r) * H + h;
+            const float bt = ld(beta + tok);
+            for (int col = lane; col < D; col += 32) {
+                const float p = sP[r * LD + col];
+                acc = fmaf(ld(v + tok * D + col), p, acc);
+                st(dv + tok * D + col, bt * p);
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0) b.DBW[ch * BT + r] = acc;
+    }
+    // D = -L_<(P R^T), H_q = L_<=(dO R^T)
+    {
+        using TMp = TileMap<BT, BT, 8, 2>;
+        float acc[8][2], acc2[8][2];
+        zero(acc);
+        zero(acc2);
+        tile_gemm<BT, BT, 8, 2>(acc, 0, D, [&](int m, int kk) { return sP[m * LD + kk]; },
+                                [&](int kk, int nn) { return sR[nn * LD + kk]; });
+        tile_gemm<BT, BT, 8, 2>(acc2, 0, D, [&](int m, int kk) { return sO[m * LD + kk]; },
+                                [&](int kk, int nn) { return sR[nn * LD + kk]; });
+        float* DM = b.DM + ch * BT * BT;
+        float* HQ = b.HQ + ch * BT * BT;
+#pragma unroll
+        for (int ii = 0; ii < 8; ++ii)
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+                const int m = TMp::row(ii), nn = TMp::col(jj);
+                DM[m * BT + nn] = (nn < m) ? -acc[ii][jj] : 0.f;
+                HQ[m * BT + nn] = (nn <= m) ? acc2[ii][jj] : 0.f;
+            }
+    }
+    // dO S^T, -P S^T, R S+bar^T over value slices; rowsum(S .* S+bar)
+    constexpr int TN = D / 32;
+    using TK = TileMap<BT, D, 8, TN>;
+    float aQ[8][TN], aP[8][TN], aF[8][TN];
+    zero(aQ);
+    zero(aP);
+    zero(aF);
+    constexpr int TPR = NTHREADS / D;          // threads per key row for the rowsum
+    const int kr = tid / TPR, kpart = tid % TPR;
+    float lam = 0.f;
+    const float* SIN = f.SIN + ch * D * D;
+    const float* SBP = b.SBP + ch * D * D;
+    for (int vs = 0; vs < D; vs += SL) {
+        __syncthreads();
+        for (int idx = tid; idx < D * SL; idx += NTHREADS) {
+            const int r = idx / SL, cc = idx % SL;
+            sS[r * LS + cc] = SIN[(size_t)r * D + vs + cc];
+            sT[r * LS + cc] = SBP[(size_t)r * D + vs + cc];
+        }
+        __syncthreads();
+        tile_gemm<BT, D, 8, TN>(aQ, 0, SL, [&](int m, int kk) { return sO[m * LD + vs + kk]; },
+                                [&](int kk, int nn) { return sS[nn * LS + kk]; });
+        tile_gemm<BT, D, 8, TN>(aP, 0, SL, [&](int m, int kk) { return sP[m * LD + vs + kk]; },
+                                [&](int kk, int nn) { return sS[nn * LS + kk]; });
+        tile_gemm<BT, D, 8, TN>(aF, 0, SL, [&](int m, int kk) { return sR[m * LD + vs + kk]; },
+                                [&](int kk, int nn) { return sT[nn * LS + kk]; });
+        for (int cc = kpart; cc < SL; cc += TPR) lam = fmaf(sS[kr * LS + cc], sT[kr * LS + cc], lam);
+    }
+    float* QS = b.QS + ch * BT * D;
+    float* PS = b.PS + ch * BT * D;
+    float* FB = b.FB + ch * BT * D;
+#pragma unroll
+    for (int ii = 0; ii < 8; ++ii)
+#pragma unroll
+        for (int jj = 0; jj < TN; ++jj) {
+            const size_t o = (size_t)TK::row(ii) * D + TK::col(jj);
+            QS[o] = aQ[ii][jj];
+            PS[o] = -aP[ii][jj];
+            FB[o] = aF[ii][jj];
+        }
+#pragma unroll
+    for (int o = TPR / 2; o > 0; o >>= 1) lam += __shfl_xor_sync(0xffffffffu, lam, o);
+    if (kpart == 0) b.LAMB[ch * D + kr] = lam;
+}
+
+template <typename TI, int D, int GATE>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    k_bwd_intra(Shape s, const TI* __restrict__ q, const TI* __restrict__ k,
+                const TI* __restrict__ beta, const float* __restrict__ g, Table t, Fwd f, Bwd b,
+                TI* __restrict__ dq, TI* __restrict__ dk, TI* __restrict__ dbeta,
+                float* __restrict__ dg) {
+    constexpr int LD = D + 1, LA = BT + 1;
+    extern __shared__ float smem[];
+    float* sK = smem;               // [BT][LD] keys
+    float* sQ = sK + BT * LD;       // [BT][LD] queries
+    float* sG = sQ + BT * LD;       // [BT][LD] cumulative log2-decay
+    float* sF3 = sG + BT * LD;      // [BT][LD] operand
+    float* sF4 = sF3 + BT * LD;     // [BT][LD] operand / G_bar
+    float* sDM = sF4 + BT * LD;     // [BT][LA] D
+    float* sHQ = sDM + BT * LA;     // [BT][LA] H_q
+    float* sBeta = sHQ + BT * LA;   // [BT]
+    float* sC = sBeta + BT;         // [D] center of each feature
+    float* sRow = sC + D;           // [BT] per-row reductions
+
+    const int c = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+    const int len = t.chunk_len[c];
+    if (len <= 0) return;
+    const int tok0 = t.chunk_tok0[c];
+    const int H = s.H;
+    const size_t ch = (size_t)c * H + h;
+    const float scale = s.scale;
+    const int lane = tid & 31, warp = tid >> 5;
+
+    for (int idx = tid; idx < BT * D; idx += NTHREADS) {
+        const int r = idx / D, col = idx % D;
+        float kv = 0.f, qv = 0.f, gv = 0.f;
+        if (r < len) {
+            const size_t off = ((size_t)(tok0 + r) * H + h) * D + col;
+            kv = ld(k + off);
+            qv = ld(q + off);
+            if (GATE == 2) gv = g[off] * LOG2E;
+            if (GATE == 1) gv = g[(size_t)(tok0 + r) * H + h] * LOG2E;
+        }
+        sK[r * LD + col] = kv;
+        sQ[r * LD + col] = qv;
+        sG[r * LD + col] = gv;
+    }
+    {
+        const float* DM = b.DM + ch * BT * BT;
+        const float* HQ = b.HQ + ch * BT * BT;
+        for (int idx = tid; idx < BT * BT; idx += NTHREADS) {
+            sDM[(idx / BT) * LA + idx % BT] = DM[idx];
+            sHQ[(idx / BT) * LA + idx % BT] = HQ[idx];
+        }
+    }
+    if (tid < BT) sBeta[tid] = (tid < len) ? ld(beta + (size_t)(tok0 + tid) * H + h) : 0.f;
+    __syncthreads();
+    int wide_col = 0;
+    if (tid < D) {
+        float acc = 0.f;
+        for (int r = 0; r < BT; ++r) {
+            acc += sG[r * LD + tid];
+            sG[r * LD + tid] = acc;
+        }
+        float hi = sG[tid], lo = sG[tid];
+        for (int r = 1; r < len; ++r) {
+            hi = fmaxf(hi, sG[r * LD + tid]);
+            lo = fminf(lo, sG[r * LD + tid]);
+        }
+        sC[tid] = (GATE == 2) ? 0.5f * (hi + lo) : 0.f;   // midpoint center
+        wide_col = (GATE == 2) && (hi - lo > CENTER_RANGE_LOG2);
+    }
+    // gate-range dispatch: one wide feature sends the chunk to the sub-chunk path
+    const bool wide = __syncthreads_or(wide_col) != 0;
+    if (GATE == 1) {
+        // scalar gate: fold the exact pairwise decay exp(G_i - G_j) (<= 1) into D and H_q
+        for (int idx = tid; idx < BT * BT; idx += NTHREADS) {
+            const int i = idx / BT, j = idx % BT;
+            if (j <= i) {
+                const float e = exp2f(sG[i * LD] - sG[j * LD]);
+                sDM[i * LA + j] *= e;
+                sHQ[i * LA + j] *= e;
+            }
+        }
+        __syncthreads();
+    }
+
+    constexpr int TN = D / 32;
+    using TK = TileMap<BT, D, 8, TN>;
+    float aQ[8][TN], aE[8][TN], aY[8][TN];
+    zero(aQ);
+    zero(aE);
+    zero(aY);
+    // factors: unit for scalar / no gate (already folded), centered otherwise
+    auto alpha = [&](int i, int col) { return GATE == 2 ? exp2f(sG[i * LD + col] - sC[col]) : 1.f; };
+    auto zeta = [&](int i, int col) { return GATE == 2 ? exp2f(sC[col] - sG[i * LD + col]) : 1.f; };
+
+    if (!wide) {
+        // T_q = H_q (K zeta), T_e = D (K zeta)
+        for (int idx = tid; idx < BT * D; idx += NTHREADS) {
+            const int r = idx / D, col = idx % D;
+            sF3[r * LD + col] = sK[r * LD + col] * zeta(r, col);
+        }
+        __syncthreads();
+        tile_gemm<BT, D, 8, TN>(aQ, 0, BT, [&](int m, int kk) { return sHQ[m * LA + kk]; },
+                                [&](int kk, int nn) { return sF3[kk * LD + nn]; });
+        tile_gemm<BT, D, 8, TN>(aE, 0, BT, [&](int m, int kk) { return sDM[m * LA + kk]; },
+                                [&](int kk, int nn) { return sF3[kk * LD + nn]; });
+#pragma unroll
+        for (int ii = 0; ii < 8; ++ii)
+#pragma unroll
+            for (int jj = 0; jj < TN; ++jj) {
+                const float a = alpha(TK::row(ii), TK::col(jj));
+                aQ[ii][jj] *= a;
+                aE[ii][jj] *= a;
+            }
+        __syncthreads();
+        // T_y = D^T (beta K alpha) + H_q^T (scale Q alpha)
+        for (int idx = tid; idx < BT * D; idx += NTHREADS) {
+            const int r = idx / D, col = idx % D;
+            const float a = alpha(r, col);
+            sF3[r * LD + col] = sBeta[r] * sK[r * LD + col] * a;
+            sF4[r * LD + col] = scale * sQ[r * LD + col] * a;
+        }
+        __syncthreads();
+        tile_gemm<BT, D, 8, TN>(aY, 0, BT, [&](int m, int kk) { return sDM[kk * LA + m]; },
+                                [&](int kk, int nn) { return sF3[kk * LD + nn]; });
+        tile_gemm<BT, D, 8, TN>(aY, 0, BT, [&](int m, int kk) { return sHQ[kk * LA + m]; },
+                                [&](int kk, int nn) { return sF4[kk * LD + nn]; });
+#pragma unroll
+        for (int ii = 0; ii < 8; ++ii)
+#pragma unroll
+            for (int jj = 0; jj < TN; ++jj) aY[ii][jj] *= zeta(TK::row(ii), TK::col(jj));
+    } else {
+        // Strong gates: 16-token sub-chunks. Receiving rows i of sub-chunk sb
+        // take earlier sub-chunks with the anchor G at the first row of sb
+        // (both factors <= 1) and the diagonal block with its midpoint row.
+        // A thread's rows in sub-chunk sb are TK::row(2 sb) and TK::row(2 sb + 1).
+        const int tm = TK::tm(), tn = TK::tn();
+        for (int sb = 0; sb < BT / BC; ++sb) {
+            if (sb * BC >= len) break;
+            const int ra = sb * BC, rm = sb * BC + BC / 2;
+            __syncthreads();
+            for (int idx = tid; idx < BT * D; idx += NTHREADS) {
+                const int j = idx / D, col = idx % D;
+                float val = 0.f;
+                if (j < ra) val = sK[j * LD + col] * exp2f(sG[ra * LD + col] - sG[j * LD + col]);
+                else if (j < ra + BC) val = sK[j * LD + col] * exp2f(sG[rm * LD + col] - sG[j * LD + col]);
+                sF3[j * LD + col] = val;
+            }
+            __syncthreads();
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {
+                const float* Mx = which == 0 ? sHQ : sDM;
+                float off[2][TN], dia[2][TN];
+                zero(off);
+                zero(dia);
+                for (int kk = 0; kk < ra + BC; ++kk) {
+                    float a[2], bv[TN];
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) a[r] = Mx[(tm + 8 * (2 * sb + r)) * LA + kk];
+#pragma unroll
+                    for (int jj = 0; jj < TN; ++jj) bv[jj] = sF3[kk * LD + tn + 32 * jj];
+#pragma unroll
+                    for (int r = 0; r < 2; ++r)
+#pragma unroll
+                        for (int jj = 0; jj < TN; ++jj) {
+                            if (kk < ra) off[r][jj] = fmaf(a[r], bv[jj], off[r][jj]);
+                            else dia[r][jj] = fmaf(a[r], bv[jj], dia[r][jj]);
+                        }
+                }
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const int i = tm + 8 * (2 * sb + r);
+#pragma unroll
+                    for (int jj = 0; jj < TN; ++jj) {
+                        const int col = tn + 32 * jj;
+                        const float gi = sG[i * LD + col];
+                        const float val = exp2f(gi - sG[ra * LD + col]) * off[r][jj] +
+                                          exp2f(gi - sG[rm * LD + col]) * dia[r][jj];
+                        if (which == 0) aQ[2 * sb + r][jj] = val;
+                        else aE[2 * sb + r][jj] = val;
+                    }
+                }
+            }
+        }
+        // Transposed contractions: output rows j of sub-chunk sb; summed rows i
+        // of later sub-chunks use the anchor G at the last row of sb, the
+        // diagonal block its midpoint row.
+        for (int sb = 0; sb < BT / BC; ++sb) {
+            if (sb * BC >= len) break;
+            const int ra = sb * BC, re = sb * BC + BC - 1, rm = sb * BC + BC / 2;
+            __syncthreads();
+            for (int idx = tid; idx < BT * D; idx += NTHREADS) {
+                const int i = idx / D, col = idx % D;
+                float e = 0.f;
+                if (i >= ra + BC) e = exp2f(sG[i * LD + col] - sG[re * LD + col]);
+                else if (i >= ra) e = exp2f(sG[i * LD + col] - sG[rm * LD + col]);
+                sF3[i * LD + col] = sBeta[i] * sK[i * LD + col] * e;
+                sF4[i * LD + col] = scale * sQ[i * LD + col] * e;
+            }
+            __syncthreads();
+            float off[2][TN], dia[2][TN];
+            zero(off);
+            zero(dia);
+            for (int kk = ra; kk < BT; ++kk) {
+                float a1[2], a2[2], b1[TN], b2[TN];
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const int j = tm + 8 * (2 * sb + r);
+                    a1[r] = sDM[kk * LA + j];
+                    a2[r] = sHQ[kk * LA + j];
+                }
+#pragma unroll
+                for (int jj = 0; jj < TN; ++jj) {
+                    b1[jj] = sF3[kk * LD + tn + 32 * jj];
+                    b2[jj] = sF4[kk * LD + tn + 32 * jj];
+                }
+#pragma unroll
+                for (int r = 0; r < 2; ++r)
+#pragma unroll
+                    for (int jj = 0; jj < TN; ++jj) {
+                        const float x = fmaf(a1[r], b1[jj], a2[r] * b2[jj]);
+                        if (kk >= ra + BC) off[r][jj] += x;
+                        else dia[r][jj] += x;
+                    }
+            }
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int j = tm + 8 * (2 * sb + r);
+#pragma unroll
+                for (int jj = 0; jj < TN; ++jj) {
+                    const int col = tn + 32 * jj;
+                    const float gj = sG[j * LD + col];
+                    aY[2 * sb + r][jj] = exp2f(sG[re * LD + col] - gj) * off[r][jj] +
+                                         exp2f(sG[rm * LD + col] - gj) * dia[r][jj];
+                }
+            }
+        }
+    }
+    __syncthreads();  // operand buffers free from here on
+
+    // ---- chain rule (a12)
+    const float* QS = b.QS + ch * BT * D;
+    const float* PS = b.PS + ch * BT * D;
+    const float* FB = b.FB + ch * BT * D;
+    const float* gl2 = sG + (len - 1) * LD;
+    float rowacc[8];
+#pragma unroll
+    for (int ii = 0; ii < 8; ++ii) rowacc[ii] = 0.f;
+#pragma unroll
+    for (int ii = 0; ii < 8; ++ii) {
+        const int m = TK::row(ii);
+#pragma unroll
+        for (int jj = 0; jj < TN; ++jj) {
+            const int col = TK::col(jj);
+            const size_t o = (size_t)m * D + col;
+            const float gm = sG[m * LD + col];
+            const float gam = exp2f(gm);
+            const float Qt = aQ[ii][jj] + gam * QS[o];                    // gamma * Q_g_bar
+            const float Et = aE[ii][jj] + gam * PS[o];                    // gamma * E_bar
+            const float Yt = aY[ii][jj] + FB[o] * exp2f(gl2[col] - gm);   // Y_bar / gamma
+            const float kv = sK[m * LD + col], qv = sQ[m * LD + col], bt = sBeta[m];
+            if (m < len) {
+                const size_t go = ((size_t)(tok0 + m) * H + h) * D + col;
+                st(dq + go, scale * Qt);
+                st(dk + go, bt * Et + Yt);
+            }
+            rowacc[ii] = fmaf(kv, Et, rowacc[ii]);
+            sF4[m * LD + col] = scale * qv * Qt + bt * kv * Et - kv * Yt;  // G_bar
+        }
+    }
+    // dbeta = <k_i, gamma E_bar_i> + <v_i, P_i>; a warp owns whole rows (TNX = 32)
+#pragma unroll
+    for (int ii = 0; ii < 8; ++ii) {
+        float x = rowacc[ii];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+        const int m = TK::row(ii);
+        if (lane == 0 && m < len)
+            st(dbeta + (size_t)(tok0 + m) * H + h, x + b.DBW[ch * BT + m]);
+    }
+    (void)warp;
+    __syncthreads();
+    if (GATE == 0) return;
+    // state endpoints at the last valid token: lambda*rowsum(S.*S+bar) + sum_i F_i .* F_bar_i
+    if (tid < D) {
+        const float glc = gl2[tid];
+        float e = exp2f(glc) * b.LAMB[ch * D + tid];
+        for (int i = 0; i < len; ++i)
+            e = fmaf(sK[i * LD + tid] * exp2f(glc - sG[i * LD + tid]), FB[(size_t)i * D + tid], e);
+        sF4[(len - 1) * LD + tid] += e;
+    }
+    __syncthreads();
+    if (GATE == 2) {
+        if (tid < D) {
+            float acc = 0.f;
+            for (int r = len - 1; r >= 0; --r) {
+                acc += sF4[r * LD + tid];
+                dg[((size_t)(tok0 + r) * H + h) * D + tid] = acc;
+            }
+        }
+    } else {
+        // scalar gate: sum features per row, then reverse cumsum over rows
+        for (int r = warp; r < BT; r += NTHREADS / 32) {
+            float x = 0.f;
+            for (int col = lane; col < D; col += 32) x += sF4[r * LD + col];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+            if (lane == 0) sRow[r] = x;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            float acc = 0.f;
+            for (int r = len - 1; r >= 0; --r) {
+                acc += sRow[r];
+                dg[(size_t)(tok0 + r) * H + h] = acc;
+            }
+        }
+    }
+}
+
+template <typename TI, int D>
+cudaError_t run_dstate(const Shape& s, const void* dout, const void* v, const void* beta, Table t,
+                       Fwd f, Bwd b, void* dv, cudaStream_t st) {
+    constexpr int LD = D + 1, LS = SL + 1;
+    constexpr size_t smem = sizeof(float) * (3 * BT * LD + 2 * D * LS);
+    auto kern = k_bwd_dstate<TI, D>;
+    cudaError_t e = set_smem_once<k_bwd_dstate<TI, D>>(smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(s.NC, s.H);
+    kern<<<grid, NTHREADS, smem, st>>>(s, (const TI*)dout, (const TI*)v, (const TI*)beta, t, f, b, (TI*)dv);
+    return cudaGetLastError();
+}
+
+template <typename TI, int D, int GATE>
+cudaError_t run_intra(const Shape& s, const void* q, const void* k, const void* beta, const float* g,
+                      Table t, Fwd f, Bwd b, void* dq, void* dk, void* dbeta, float* dg,
+                      cudaStream_t st) {
+    constexpr int LD = D + 1, LA = BT + 1;
+    constexpr size_t smem = sizeof(float) * (5 * BT * LD + 2 * BT * LA + 2 * BT + D);
+    auto kern = k_bwd_intra<TI, D, GATE>;
+    cudaError_t e = set_smem_once<k_bwd_intra<TI, D, GATE>>(smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(s.NC, s.H);
+    kern<<<grid, NTHREADS, smem, st>>>(s, (const TI*)q, (const TI*)k, (const TI*)beta, g, t, f, b,
+                                       (TI*)dq, (TI*)dk, (TI*)dbeta, dg);
+    return cudaGetLastError();
+}
+
+template <typename TI, int D>
+cudaError_t run_intra_gate(int gate, const Shape& s, const void* q, const void* k, const void* beta,
+                           const float* g, Table t, Fwd f, Bwd b, void* dq, void* dk, void* dbeta,
+                           float* dg, cudaStream_t st) {
+    switch (gate) {
+        case 0: return run_intra<TI, D, 0>(s, q, k, beta, g, t, f, b, dq, dk, dbeta, dg, st);
+        case 1: return run_intra<TI, D, 1>(s, q, k, beta, g, t, f, b, dq, dk, dbeta, dg, st);
+        default: return run_intra<TI, D, 2>(s, q, k, beta, g, t, f, b, dq, dk, dbeta, dg, st);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_dstate(const Shape& s, int io_bf16, const void* dout, const void* v,
+                              const void* beta, Table t, Fwd f, Bwd b, void* dv, cudaStream_t st) {
+    if (s.K == 128)
+        return io_bf16 ? run_dstate<__nv_bfloat16, 128>(s, dout, v, beta, t, f, b, dv, st)
+                       : run_dstate<float, 128>(s, dout, v, beta, t, f, b, dv, st);
+    return io_bf16 ? run_dstate<__nv_bfloat16, 64>(s, dout, v, beta, t, f, b, dv, st)
+                   : run_dstate<float, 64>(s, dout, v, beta, t, f, b, dv, st);
+}
+
+cudaError_t launch_bwd_intra(const Shape& s, int io_bf16, int gate, const void* q, const void* k,
+                             const void* beta, const float* g, Table t, Fwd f, Bwd b, void* dq,
+                             void* dk, void* dbeta, float* dg, cudaStream_t st) {
+    if (s.K == 128)
+        return io_bf16 ? run_intra_gate<__nv_bfloat16, 128>(gate, s, q, k, beta, g, t, f, b, dq, dk, dbeta, dg, st)
+                       : run_intra_gate<float, 128>(gate, s, q, k, beta, g, t, f, b, dq, dk, dbeta, dg, st);
+    return io_bf16 ? run_intra_gate<__nv_bfloat16, 64>(gate, s, q, k, beta, g, t, f, b, dq, dk, dbeta, dg, st)
+                   : run_intra_gate<float, 64>(gate, s, q, k, beta, g, t, f, b, dq, dk, dbeta, dg, st);
+}
+
+}  // namespace kda

@@ -1,0 +1,152 @@
+// Internal declarations shared by the CUDA translation units of libkda.so.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kda {
+
+constexpr int BT = 64;        // chunk length C
+constexpr int BC = 16;        // sub-chunk length used by the strong-gate path
+constexpr int NTHREADS = 256; // threads per CTA for every kernel
+
+// Gate-range threshold of the centered matrix-intra path, in log2 units: a
+// chunk whose per-feature range of cumulative log2-decay exceeds it takes the
+// 16-token anchored path instead.
+constexpr float CENTER_RANGE_LOG2 = 80.0f;
+
+constexpr float LOG2E = 1.4426950408889634f;
+
+// Chunk bookkeeping built on the device from cu_seqlens (or from B, T).
+struct Table {
+    int32_t* chunk_tok0;  // [NC] first token of the chunk (packed axis)
+    int32_t* chunk_len;   // [NC] tokens in the chunk; 0 marks an unused slot
+    int32_t* seq_chunk0;  // [N+1] first chunk slot of each sequence
+    int32_t* seq_tok0;    // [N] first token of each sequence
+    int32_t* seq_len;     // [N] tokens of each sequence
+    int32_t* err;         // [1] device error word
+};
+
+// Forward chunk intermediates, fp32, one block per (chunk slot, head).
+struct Fwd {
+    float* W;     // [NC,H,BT,K]  A E
+    float* U;     // [NC,H,BT,V]  A Z
+    float* KG;    // [NC,H,BT,K]  F = keys decayed to the chunk end
+    float* QG;    // [NC,H,BT,K]  Q_g = scale q decayed from the chunk start
+    float* AQK;   // [NC,H,BT,BT] C_q
+    float* AINV;  // [NC,H,BT,BT] A = (I + L)^-1
+    float* GL;    // [NC,H,K]     cumulative log2-decay at the chunk's last token
+    float* R;     // [NC,H,BT,V]  corrections R (filled by the recompute scan)
+    float* SIN;   // [NC,H,K,V]   state entering the chunk (recompute scan)
+};
+
+// Backward chunk intermediates, fp32.
+struct Bwd {
+    float* P;     // [NC,H,BT,V]  shared sensitivity A^T R_bar
+    float* SBP;   // [NC,H,K,V]   adjoint of the state leaving the chunk
+    float* QS;    // [NC,H,BT,K]  dO S^T
+    float* PS;    // [NC,H,BT,K]  -P S^T
+    float* FB;    // [NC,H,BT,K]  R S+bar^T
+    float* DM;    // [NC,H,BT,BT] D = -L_<(P R^T)
+    float* HQ;    // [NC,H,BT,BT] H_q = L_<=(dO R^T)
+    float* LAMB;  // [NC,H,K]     rowsum(S .* S+bar)
+    float* DBW;   // [NC,H,BT]    <v_i, P_i>
+};
+
+struct Shape {
+    int H, K, V;
+    int N;        // sequences
+    int NC;       // chunk slots (upper bound)
+    int Ttot;     // tokens on the packed axis
+    float scale;
+};
+
+// ---------------------------------------------------------------- element I/O
+__device__ __forceinline__ float ld(const float* p) { return *p; }
+__device__ __forceinline__ float ld(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+__device__ __forceinline__ void st(float* p, float x) { *p = x; }
+__device__ __forceinline__ void st(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
+
+// ------------------------------------------------------- CUDA-core tile GEMM
+// acc[i][j] += sum_{kk < Kdim} A(m_i, kk) * B(kk, n_j) over the calling
+// thread's share of an M x N tile: threads are laid out TMX x TNX with
+// TNX = N / TN lanes along n (consecutive lanes take consecutive n), and the
+// thread's rows / columns are strided: m_i = tm + i*TMX, n_j = tn + j*TNX.
+// A and B are callables reading shared memory.
+template <int M, int N, int TM, int TN>
+struct TileMap {
+    static constexpr int TNX = N / TN;
+    static constexpr int TMX = M / TM;
+    static_assert(TNX * TMX == NTHREADS, "tile shape must use every thread");
+    __device__ __forceinline__ static int tn() { return threadIdx.x % TNX; }
+    __device__ __forceinline__ static int tm() { return threadIdx.x / TNX; }
+    __device__ __forceinline__ static int row(int i) { return tm() + i * TMX; }
+    __device__ __forceinline__ static int col(int j) { return tn() + j * TNX; }
+};
+
+template <int M, int N, int TM, int TN, class FA, class FB>
+__device__ __forceinline__ void tile_gemm(float (&acc)[TM][TN], int k0, int k1, FA A, FB B) {
+    using TMp = TileMap<M, N, TM, TN>;
+    const int tm = TMp::tm(), tn = TMp::tn();
+#pragma unroll 2
+    for (int kk = k0; kk < k1; ++kk) {
+        float a[TM], b[TN];
+#pragma unroll
+        for (int i = 0; i < TM; ++i) a[i] = A(tm + i * TMp::TMX, kk);
+#pragma unroll
+        for (int j = 0; j < TN; ++j) b[j] = B(kk, tn + j * TMp::TNX);
+#pragma unroll
+        for (int i = 0; i < TM; ++i)
+#pragma unroll
+            for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+}
+
+template <int TM, int TN>
+__device__ __forceinline__ void zero(float (&acc)[TM][TN]) {
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
+}
+
+// Raises a kernel's dynamic shared-memory limit once per device (so that no
+// attribute call is issued again once a stream is being captured).
+template <auto Kern>
+inline cudaError_t set_smem_once(size_t bytes) {
+    static int done[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+    e = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = 1;
+    return e;
+}
+
+// --------------------------------------------------------------- launchers
+// Each returns cudaSuccess or the launch error. Defined in the .cu files.
+cudaError_t launch_table(const Shape& s, int B, int T, const int32_t* cu, Table t, cudaStream_t st);
+
+cudaError_t launch_prep(const Shape& s, int io_bf16, int gate, const void* q, const void* k,
+                        const void* v, const void* beta, const float* g, Table t, Fwd f,
+                        cudaStream_t st);
+
+// mode bit 0: write o; bit 1: write R and SIN for the backward pass.
+cudaError_t launch_fwd_scan(const Shape& s, int io_bf16, int mode, const float* h0, Table t,
+                            Fwd f, void* o, float* ht, cudaStream_t st);
+
+cudaError_t launch_bwd_scan(const Shape& s, int io_bf16, const void* dout, const float* dht,
+                            Table t, Fwd f, Bwd b, float* dh0, cudaStream_t st);
+
+cudaError_t launch_bwd_dstate(const Shape& s, int io_bf16, const void* dout, const void* v,
+                              const void* beta, Table t, Fwd f, Bwd b, void* dv,
+                              cudaStream_t st);
+
+cudaError_t launch_bwd_intra(const Shape& s, int io_bf16, int gate, const void* q,
+                             const void* k, const void* beta, const float* g, Table t, Fwd f,
+                             Bwd b, void* dq, void* dk, void* dbeta, float* dg,
+                             cudaStream_t st);
+
+}  // namespace kda

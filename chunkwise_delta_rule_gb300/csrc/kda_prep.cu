@@ -1,0 +1,215 @@
+// Chunk-parallel forward preparation, one CTA per (chunk slot, head):
+//   a1  in-chunk cumulative log2-decay G2 = cumsum(g) / ln 2 (exp2(G2) = exp(G))
+//   a2  L = Akk = L_<(E Y^T) (strict) and C_q = Aqk = L_<=(Q_g Y^T) (inclusive)
+//   a3  A = (I + L)^-1
+//   a4  W = A E, U = A Z, F = keys decayed to the chunk end, Q_g
+// ("ReWY" paper: "The chunk system and conventional WY backward"; "Kimi Delta
+// Attention" blog, sections 6.3-6.6; GatedDeltaNet-2 spec transcription,
+// sections 2.1-2.5 for the base-2 cumsum, the sub-chunk anchoring and the
+// u/w auxiliaries).
+//
+// Numerics: the pairwise decay exp(G_i - G_j) is split into a row factor and
+// a column factor anchored at the midpoint row of the receiving 16-token
+// sub-chunk, so factors stay within exp(8 |g|max) and products never
+// overflow; A is built in fp32 by column-parallel forward substitution.
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+template <typename TI, int D, int GATE>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    k_prep(Shape s, const TI* __restrict__ q, const TI* __restrict__ k, const TI* __restrict__ v,
+           const TI* __restrict__ beta, const float* __restrict__ g, Table t, Fwd f) {
+    constexpr int LD = D + 1;       // padded row stride of [BT x D] tiles
+    constexpr int LA = BT + 1;      // padded row stride of [BT x BT] tiles
+    extern __shared__ float smem[];
+    float* sK = smem;               // [BT][LD] keys (fp32)
+    float* sG = sK + BT * LD;       // [BT][LD] cumulative log2-decay
+    float* sQ = sG + BT * LD;       // [BT][LD] queries, later beta*v
+    float* sL = sQ + BT * LD;       // [2*BC][LD] row factors
+    float* sR = sL + 2 * BC * LD;   // [BT][LD] column factors / E
+    float* sAkk = sR + BT * LD;     // [BT][LA]
+    float* sAi = sAkk + BT * LA;    // [BT][LA]
+    float* sBeta = sAi + BT * LA;   // [BT]
+
+    const int c = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+    const int n = t.chunk_len[c];
+    if (n <= 0) return;
+    const int tok0 = t.chunk_tok0[c];
+    const int H = s.H;
+    const size_t ch = (size_t)c * H + h;
+
+    // ---- load chunk rows (rows >= n are zero keys/queries and zero decay)
+    for (int idx = tid; idx < BT * D; idx += NTHREADS) {
+        const int r = idx / D, col = idx % D;
+        float kv = 0.f, qv = 0.f, gv = 0.f;
+        if (r < n) {
+            const size_t off = ((size_t)(tok0 + r) * H + h) * D + col;
+            kv = ld(k + off);
+            qv = ld(q + off);
+            if (GATE == 2) gv = g[off] * LOG2E;
+            if (GATE == 1) gv = g[(size_t)(tok0 + r) * H + h] * LOG2E;
+        }
+        sK[r * LD + col] = kv;
+        sQ[r * LD + col] = qv;
+        sG[r * LD + col] = gv;
+    }
+    if (tid < BT) sBeta[tid] = (tid < n) ? ld(beta + (size_t)(tok0 + tid) * H + h) : 0.f;
+    __syncthreads();
+    // ---- a1: inclusive cumsum down each feature column (padding rows keep G[n-1])
+    if (tid < D) {
+        float acc = 0.f;
+        for (int r = 0; r < BT; ++r) {
+            acc += sG[r * LD + tid];
+            sG[r * LD + tid] = acc;
+        }
+    }
+    __syncthreads();
+
+    // ---- a2: Akk and Aqk, one 16-row sub-chunk of receiving rows at a time
+    const float scale = s.scale;
+    float* AQK = f.AQK + ch * BT * BT;
+    for (int b = 0; b < BT / BC; ++b) {
+        const int ra = b * BC + BC / 2;          // anchor row (padding rows repeat G[n-1])
+        const int ncol = (b + 1) * BC;           // columns j that can be <= i
+        for (int idx = tid; idx < 2 * BC * D; idx += NTHREADS) {
+            const int r = idx / D, col = idx % D;
+            const int i = b * BC + (r & (BC - 1));
+            const float e = exp2f(sG[i * LD + col] - sG[ra * LD + col]);
+            sL[r * LD + col] = (r < BC) ? sBeta[i] * sK[i * LD + col] * e : scale * sQ[i * LD + col] * e;
+        }
+        for (int idx = tid; idx < ncol * D; idx += NTHREADS) {
+            const int j = idx / D, col = idx % D;
+            sR[j * LD + col] = sK[j * LD + col] * exp2f(sG[ra * LD + col] - sG[j * LD + col]);
+        }
+        __syncthreads();
+        float acc[4][2];
+        zero(acc);
+        tile_gemm<2 * BC, BT, 4, 2>(
+            acc, 0, D, [&](int m, int kk) { return sL[m * LD + kk]; },
+            [&](int kk, int nn) { return nn < ncol ? sR[nn * LD + kk] : 0.f; });
+        using TMp = TileMap<2 * BC, BT, 4, 2>;
+#pragma unroll
+        for (int ii = 0; ii < 4; ++ii) {
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+                const int r = TMp::row(ii), j = TMp::col(jj);
+                const int i = b * BC + (r & (BC - 1));
+                if (r < BC) {
+                    sAkk[i * LA + j] = (j < i && i < n) ? acc[ii][jj] : 0.f;
+                } else {
+                    AQK[i * BT + j] = (j <= i && i < n) ? acc[ii][jj] : 0.f;
+                }
+            }
+        }
+        __syncthreads();
+    }
+
+    // ---- a3: A = (I + Akk)^-1 by forward substitution; 4 lanes per column
+    {
+        const int col = tid >> 2, part = tid & 3;
+        for (int r = part; r < BT; r += 4) sAi[r * LA + col] = (r == col) ? 1.f : 0.f;
+        __syncwarp();
+        for (int i = 1; i < BT; ++i) {
+            float acc = 0.f;
+            if (i > col) {
+                for (int j = col + part; j < i; j += 4) acc = fmaf(sAkk[i * LA + j], sAi[j * LA + col], acc);
+            }
+            acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+            acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+            if (part == 0 && i > col) sAi[i * LA + col] = -acc;
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+
+    // ---- a4: Q_g, F (keys to chunk end), G at the last token
+    {
+        const float* gl = sG + (n - 1) * LD;
+        float* QG = f.QG + ch * BT * D;
+        float* KG = f.KG + ch * BT * D;
+        for (int idx = tid; idx < BT * D; idx += NTHREADS) {
+            const int r = idx / D, col = idx % D;
+            const float gr = sG[r * LD + col];
+            QG[idx] = scale * sQ[r * LD + col] * exp2f(gr);
+            KG[idx] = sK[r * LD + col] * exp2f(gl[col] - gr);
+        }
+        if (tid < D) f.GL[ch * D + tid] = gl[tid];
+        float* AI = f.AINV + ch * BT * BT;
+        for (int idx = tid; idx < BT * BT; idx += NTHREADS) AI[idx] = sAi[(idx / BT) * LA + idx % BT];
+    }
+    // E = diag(beta) K exp(G) into sR; beta*v into sQ
+    for (int idx = tid; idx < BT * D; idx += NTHREADS) {
+        const int r = idx / D, col = idx % D;
+        sR[r * LD + col] = sBeta[r] * sK[r * LD + col] * exp2f(sG[r * LD + col]);
+    }
+    __syncthreads();  // all reads of sQ (queries) are done
+    for (int idx = tid; idx < BT * D; idx += NTHREADS) {
+        const int r = idx / D, col = idx % D;
+        sQ[r * LD + col] = (r < n) ? sBeta[r] * ld(v + ((size_t)(tok0 + r) * H + h) * D + col) : 0.f;
+    }
+    __syncthreads();
+    constexpr int TN = D / 32;
+    using TM8 = TileMap<BT, D, 8, TN>;
+    {
+        float acc[8][TN];
+        zero(acc);
+        tile_gemm<BT, D, 8, TN>(acc, 0, BT, [&](int m, int kk) { return sAi[m * LA + kk]; },
+                                [&](int kk, int nn) { return sR[kk * LD + nn]; });
+        float* W = f.W + ch * BT * D;
+#pragma unroll
+        for (int ii = 0; ii < 8; ++ii)
+#pragma unroll
+            for (int jj = 0; jj < TN; ++jj) W[TM8::row(ii) * D + TM8::col(jj)] = acc[ii][jj];
+    }
+    {
+        float acc[8][TN];
+        zero(acc);
+        tile_gemm<BT, D, 8, TN>(acc, 0, BT, [&](int m, int kk) { return sAi[m * LA + kk]; },
+                                [&](int kk, int nn) { return sQ[kk * LD + nn]; });
+        float* U = f.U + ch * BT * D;
+#pragma unroll
+        for (int ii = 0; ii < 8; ++ii)
+#pragma unroll
+            for (int jj = 0; jj < TN; ++jj) U[TM8::row(ii) * D + TM8::col(jj)] = acc[ii][jj];
+    }
+}
+
+template <typename TI, int D, int GATE>
+cudaError_t run(const Shape& s, const void* q, const void* k, const void* v, const void* beta,
+                const float* g, Table t, Fwd f, cudaStream_t st) {
+    constexpr int LD = D + 1, LA = BT + 1;
+    constexpr size_t smem = sizeof(float) * (3 * BT * LD + 2 * BC * LD + BT * LD + 2 * BT * LA + BT);
+    auto kern = k_prep<TI, D, GATE>;
+    cudaError_t e = set_smem_once<k_prep<TI, D, GATE>>(smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(s.NC, s.H);
+    kern<<<grid, NTHREADS, smem, st>>>(s, (const TI*)q, (const TI*)k, (const TI*)v, (const TI*)beta, g, t, f);
+    return cudaGetLastError();
+}
+
+template <typename TI, int D>
+cudaError_t run_gate(int gate, const Shape& s, const void* q, const void* k, const void* v,
+                     const void* beta, const float* g, Table t, Fwd f, cudaStream_t st) {
+    switch (gate) {
+        case 0: return run<TI, D, 0>(s, q, k, v, beta, g, t, f, st);
+        case 1: return run<TI, D, 1>(s, q, k, v, beta, g, t, f, st);
+        default: return run<TI, D, 2>(s, q, k, v, beta, g, t, f, st);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_prep(const Shape& s, int io_bf16, int gate, const void* q, const void* k,
+                        const void* v, const void* beta, const float* g, Table t, Fwd f,
+                        cudaStream_t st) {
+    if (s.K == 128) {
+        return io_bf16 ? run_gate<__nv_bfloat16, 128>(gate, s, q, k, v, beta, g, t, f, st)
+                       : run_gate<float, 128>(gate, s, q, k, v, beta, g, t, f, st);
+    }
+    return io_bf16 ? run_gate<__nv_bfloat16, 64>(gate, s, q, k, v, beta, g, t, f, st)
+                   : run_gate<float, 64>(gate, s, q, k, v, beta, g, t, f, st);
+}
+
+}  // namespace kda

@@ -1,0 +1,276 @@
+// Inter-chunk state scans, one CTA per (sequence, head, value tile), serial
+// over the sequence's chunks; the state tile S[:, tile] stays in shared memory
+// in fp32 for the whole sequence.
+//
+// Forward (a5 + a6; "ReWY" paper, "The chunk system and conventional WY
+// backward"; "Kimi Delta Attention" blog, sections 6.4-6.5):
+//     R = U - W S ;  O = Q_g S + C_q R ;  S <- diag(lambda) S + F^T R
+// Reverse (a8; "ReWY" paper, "State and gate composition" and "Complete
+// Reverse Execution and Boundaries"):
+//     R_bar = C_q^T dO + F S+bar ;  P = A^T R_bar ;
+//     S_bar <- diag(lambda) S+bar + Q_g^T dO - W^T R_bar
+// where -W^T R_bar = -E^T P is the residual state term, supplied once here.
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int VT = 32;  // value columns per CTA
+
+template <typename TI, int D, int MODE>
+__global__ void __launch_bounds__(NTHREADS)
+    k_fwd_scan(Shape s, const float* __restrict__ h0, Table t, Fwd f, TI* __restrict__ o,
+               float* __restrict__ ht) {
+    constexpr int LD = D + 1, LV = VT + 1, LA = BT + 1;
+    extern __shared__ float smem[];
+    float* sS = smem;             // [D][LV] state tile
+    float* sM = sS + D * LV;      // [BT][LD] W, then Q_g, then F
+    float* sR = sM + BT * LD;     // [BT][LV] U, then R
+    float* sA = sR + BT * LV;     // [BT][LA] C_q
+    float* sLam = sA + BT * LA;   // [D]
+
+    const int nseq = blockIdx.x, h = blockIdx.y, v0 = blockIdx.z * VT, tid = threadIdx.x;
+    const int H = s.H;
+    const size_t st_off = ((size_t)nseq * H + h) * D * D;
+    for (int idx = tid; idx < D * VT; idx += NTHREADS) {
+        const int r = idx / VT, cc = idx % VT;
+        sS[r * LV + cc] = h0 ? h0[st_off + (size_t)r * D + v0 + cc] : 0.f;
+    }
+    const int c0 = t.seq_chunk0[nseq], c1 = t.seq_chunk0[nseq + 1];
+    using TR = TileMap<BT, VT, 8, 1>;
+    using TS = TileMap<D, VT, D / 8, 1>;
+    for (int c = c0; c < c1; ++c) {
+        const size_t ch = (size_t)c * H + h;
+        const int len = t.chunk_len[c], tok0 = t.chunk_tok0[c];
+        const float* W = f.W + ch * BT * D;
+        const float* U = f.U + ch * BT * D;
+        for (int idx = tid; idx < BT * D; idx += NTHREADS) sM[(idx / D) * LD + idx % D] = W[idx];
+        for (int idx = tid; idx < BT * VT; idx += NTHREADS) {
+            const int r = idx / VT, cc = idx % VT;
+            sR[r * LV + cc] = U[(size_t)r * D + v0 + cc];
+        }
+        if (tid < D) sLam[tid] = exp2f(f.GL[ch * D + tid]);
+        __syncthreads();
+        // R = U - W S
+        {
+            float acc[8][1];
+            zero(acc);
+            tile_gemm<BT, VT, 8, 1>(acc, 0, D, [&](int m, int kk) { return sM[m * LD + kk]; },
+                                    [&](int kk, int nn) { return sS[kk * LV + nn]; });
+#pragma unroll
+            for (int ii = 0; ii < 8; ++ii) {
+                const int m = TR::row(ii), nn = TR::col(0);
+                const float r = sR[m * LV + nn] - acc[ii][0];
+                sR[m * LV + nn] = r;
+                if (MODE & 2) f.R[ch * BT * D + (size_t)m * D + v0 + nn] = r;
+            }
+        }
+        if (MODE & 2) {
+            float* SIN = f.SIN + ch * D * D;
+            for (int idx = tid; idx < D * VT; idx += NTHREADS) {
+                const int r = idx / VT, cc = idx % VT;
+                SIN[(size_t)r * D + v0 + cc] = sS[r * LV + cc];
+            }
+        }
+        __syncthreads();
+        if (MODE & 1) {
+            const float* QG = f.QG + ch * BT * D;
+            const float* AQK = f.AQK + ch * BT * BT;
+            for (int idx = tid; idx < BT * D; idx += NTHREADS) sM[(idx / D) * LD + idx % D] = QG[idx];
+            for (int idx = tid; idx < BT * BT; idx += NTHREADS) sA[(idx / BT) * LA + idx % BT] = AQK[idx];
+            __syncthreads();
+            float acc[8][1];
+            zero(acc);
+            tile_gemm<BT, VT, 8, 1>(acc, 0, D, [&](int m, int kk) { return sM[m * LD + kk]; },
+                                    [&](int kk, int nn) { return sS[kk * LV + nn]; });
+            tile_gemm<BT, VT, 8, 1>(acc, 0, BT, [&](int m, int kk) { return sA[m * LA + kk]; },
+                                    [&](int kk, int nn) { return sR[kk * LV + nn]; });
+#pragma unroll
+            for (int ii = 0; ii < 8; ++ii) {
+                const int m = TR::row(ii), nn = TR::col(0);
+                if (m < len) st(o + ((size_t)(tok0 + m) * H + h) * D + v0 + nn, acc[ii][0]);
+            }
+            __syncthreads();
+        }
+        {
+            const float* KG = f.KG + ch * BT * D;
+            for (int idx = tid; idx < BT * D; idx += NTHREADS) sM[(idx / D) * LD + idx % D] = KG[idx];
+            __syncthreads();
+            float acc[D / 8][1];
+            zero(acc);
+            tile_gemm<D, VT, D / 8, 1>(acc, 0, BT, [&](int m, int kk) { return sM[kk * LD + m]; },
+                                       [&](int kk, int nn) { return sR[kk * LV + nn]; });
+#pragma unroll
+            for (int ii = 0; ii < D / 8; ++ii) {
+                const int m = TS::row(ii), nn = TS::col(0);
+                sS[m * LV + nn] = sLam[m] * sS[m * LV + nn] + acc[ii][0];
+            }
+        }
+        __syncthreads();
+    }
+    if (ht) {
+        for (int idx = tid; idx < D * VT; idx += NTHREADS) {
+            const int r = idx / VT, cc = idx % VT;
+            ht[st_off + (size_t)r * D + v0 + cc] = sS[r * LV + cc];
+        }
+    }
+}
+
+template <typename TI, int D>
+__global__ void __launch_bounds__(NTHREADS)
+    k_bwd_scan(Shape s, const TI* __restrict__ dout, const float* __restrict__ dht, Table t, Fwd f,
+               Bwd b, float* __restrict__ dh0) {
+    constexpr int LD = D + 1, LV = VT + 1, LA = BT + 1;
+    extern __shared__ float smem[];
+    float* sSb = smem;             // [D][LV] state adjoint tile
+    float* sM1 = sSb + D * LV;     // [BT][LD] F, then Q_g
+    float* sM2 = sM1 + BT * LD;    // [BT][LD] W
+    float* sO = sM2 + BT * LD;     // [BT][LV] dO tile
+    float* sRb = sO + BT * LV;     // [BT][LV] R_bar
+    float* sA = sRb + BT * LV;     // [BT][LA] C_q, then A
+    float* sLam = sA + BT * LA;    // [D]
+
+    const int nseq = blockIdx.x, h = blockIdx.y, v0 = blockIdx.z * VT, tid = threadIdx.x;
+    const int H = s.H;
+    const size_t st_off = ((size_t)nseq * H + h) * D * D;
+    for (int idx = tid; idx < D * VT; idx += NTHREADS) {
+        const int r = idx / VT, cc = idx % VT;
+        sSb[r * LV + cc] = dht ? dht[st_off + (size_t)r * D + v0 + cc] : 0.f;
+    }
+    const int c0 = t.seq_chunk0[nseq], c1 = t.seq_chunk0[nseq + 1];
+    using TR = TileMap<BT, VT, 8, 1>;
+    using TS = TileMap<D, VT, D / 8, 1>;
+    for (int c = c1 - 1; c >= c0; --c) {
+        const size_t ch = (size_t)c * H + h;
+        const int len = t.chunk_len[c], tok0 = t.chunk_tok0[c];
+        {
+            const float* KG = f.KG + ch * BT * D;
+            const float* W = f.W + ch * BT * D;
+            const float* AQK = f.AQK + ch * BT * BT;
+            for (int idx = tid; idx < BT * D; idx += NTHREADS) {
+                sM1[(idx / D) * LD + idx % D] = KG[idx];
+                sM2[(idx / D) * LD + idx % D] = W[idx];
+            }
+            for (int idx = tid; idx < BT * BT; idx += NTHREADS) sA[(idx / BT) * LA + idx % BT] = AQK[idx];
+            for (int idx = tid; idx < BT * VT; idx += NTHREADS) {
+                const int r = idx / VT, cc = idx % VT;
+                sO[r * LV + cc] = (r < len) ? ld(dout + ((size_t)(tok0 + r) * H + h) * D + v0 + cc) : 0.f;
+            }
+            if (tid < D) sLam[tid] = exp2f(f.GL[ch * D + tid]);
+        }
+        __syncthreads();
+        // R_bar = C_q^T dO + F S+bar ; record S+bar for the consumers
+        {
+            float acc[8][1];
+            zero(acc);
+            tile_gemm<BT, VT, 8, 1>(acc, 0, BT, [&](int m, int kk) { return sA[kk * LA + m]; },
+                                    [&](int kk, int nn) { return sO[kk * LV + nn]; });
+            tile_gemm<BT, VT, 8, 1>(acc, 0, D, [&](int m, int kk) { return sM1[m * LD + kk]; },
+                                    [&](int kk, int nn) { return sSb[kk * LV + nn]; });
+#pragma unroll
+            for (int ii = 0; ii < 8; ++ii) sRb[TR::row(ii) * LV + TR::col(0)] = acc[ii][0];
+            float* SBP = b.SBP + ch * D * D;
+            for (int idx = tid; idx < D * VT; idx += NTHREADS) {
+                const int r = idx / VT, cc = idx % VT;
+                SBP[(size_t)r * D + v0 + cc] = sSb[r * LV + cc];
+            }
+        }
+        __syncthreads();
+        {
+            const float* AI = f.AINV + ch * BT * BT;
+            const float* QG = f.QG + ch * BT * D;
+            for (int idx = tid; idx < BT * BT; idx += NTHREADS) sA[(idx / BT) * LA + idx % BT] = AI[idx];
+            for (int idx = tid; idx < BT * D; idx += NTHREADS) sM1[(idx / D) * LD + idx % D] = QG[idx];
+        }
+        __syncthreads();
+        // P = A^T R_bar
+        {
+            float acc[8][1];
+            zero(acc);
+            tile_gemm<BT, VT, 8, 1>(acc, 0, BT, [&](int m, int kk) { return sA[kk * LA + m]; },
+                                    [&](int kk, int nn) { return sRb[kk * LV + nn]; });
+            float* P = b.P + ch * BT * D;
+#pragma unroll
+            for (int ii = 0; ii < 8; ++ii) P[(size_t)TR::row(ii) * D + v0 + TR::col(0)] = acc[ii][0];
+        }
+        // S_bar = diag(lambda) S+bar + Q_g^T dO - W^T R_bar
+        {
+            float acc[D / 8][1], acc2[D / 8][1];
+            zero(acc);
+            zero(acc2);
+            tile_gemm<D, VT, D / 8, 1>(acc, 0, BT, [&](int m, int kk) { return sM1[kk * LD + m]; },
+                                       [&](int kk, int nn) { return sO[kk * LV + nn]; });
+            tile_gemm<D, VT, D / 8, 1>(acc2, 0, BT, [&](int m, int kk) { return sM2[kk * LD + m]; },
+                                       [&](int kk, int nn) { return sRb[kk * LV + nn]; });
+#pragma unroll
+            for (int ii = 0; ii < D / 8; ++ii) {
+                const int m = TS::row(ii), nn = TS::col(0);
+                sSb[m * LV + nn] = sLam[m] * sSb[m * LV + nn] + acc[ii][0] - acc2[ii][0];
+            }
+        }
+        __syncthreads();
+    }
+    if (dh0) {
+        for (int idx = tid; idx < D * VT; idx += NTHREADS) {
+            const int r = idx / VT, cc = idx % VT;
+            dh0[st_off + (size_t)r * D + v0 + cc] = sSb[r * LV + cc];
+        }
+    }
+}
+
+template <typename TI, int D, int MODE>
+cudaError_t run_fwd(const Shape& s, const float* h0, Table t, Fwd f, void* o, float* ht, cudaStream_t st) {
+    constexpr int LD = D + 1, LV = VT + 1, LA = BT + 1;
+    constexpr size_t smem = sizeof(float) * (D * LV + BT * LD + BT * LV + BT * LA + D);
+    auto kern = k_fwd_scan<TI, D, MODE>;
+    cudaError_t e = set_smem_once<k_fwd_scan<TI, D, MODE>>(smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(s.N, s.H, D / VT);
+    kern<<<grid, NTHREADS, smem, st>>>(s, h0, t, f, (TI*)o, ht);
+    return cudaGetLastError();
+}
+
+template <typename TI, int D>
+cudaError_t run_fwd_mode(int mode, const Shape& s, const float* h0, Table t, Fwd f, void* o,
+                         float* ht, cudaStream_t st) {
+    switch (mode) {
+        case 1: return run_fwd<TI, D, 1>(s, h0, t, f, o, ht, st);
+        case 2: return run_fwd<TI, D, 2>(s, h0, t, f, o, ht, st);
+        default: return run_fwd<TI, D, 3>(s, h0, t, f, o, ht, st);
+    }
+}
+
+template <typename TI, int D>
+cudaError_t run_bwd(const Shape& s, const void* dout, const float* dht, Table t, Fwd f, Bwd b,
+                    float* dh0, cudaStream_t st) {
+    constexpr int LD = D + 1, LV = VT + 1, LA = BT + 1;
+    constexpr size_t smem = sizeof(float) * (D * LV + 2 * BT * LD + 2 * BT * LV + BT * LA + D);
+    auto kern = k_bwd_scan<TI, D>;
+    cudaError_t e = set_smem_once<k_bwd_scan<TI, D>>(smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(s.N, s.H, D / VT);
+    kern<<<grid, NTHREADS, smem, st>>>(s, (const TI*)dout, dht, t, f, b, dh0);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_scan(const Shape& s, int io_bf16, int mode, const float* h0, Table t,
+                            Fwd f, void* o, float* ht, cudaStream_t st) {
+    if (s.K == 128)
+        return io_bf16 ? run_fwd_mode<__nv_bfloat16, 128>(mode, s, h0, t, f, o, ht, st)
+                       : run_fwd_mode<float, 128>(mode, s, h0, t, f, o, ht, st);
+    return io_bf16 ? run_fwd_mode<__nv_bfloat16, 64>(mode, s, h0, t, f, o, ht, st)
+                   : run_fwd_mode<float, 64>(mode, s, h0, t, f, o, ht, st);
+}
+
+cudaError_t launch_bwd_scan(const Shape& s, int io_bf16, const void* dout, const float* dht,
+                            Table t, Fwd f, Bwd b, float* dh0, cudaStream_t st) {
+    if (s.K == 128)
+        return io_bf16 ? run_bwd<__nv_bfloat16, 128>(s, dout, dht, t, f, b, dh0, st)
+                       : run_bwd<float, 128>(s, dout, dht, t, f, b, dh0, st);
+    return io_bf16 ? run_bwd<__nv_bfloat16, 64>(s, dout, dht, t, f, b, dh0, st)
+                   : run_bwd<float, 64>(s, dout, dht, t, f, b, dh0, st);
+}
+
+}  // namespace kda

@@ -1,0 +1,86 @@
+// Chunk table: maps chunk slots to (first token, length) and sequences to
+// their chunk ranges, from cu_seqlens on the device (no host copy needed) or
+// from (B, T) for equal-length batches. Chunks restart at every sequence
+// start; the last chunk of a sequence holds the remainder (1..64 tokens).
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int TBL_THREADS = 1024;
+
+__global__ void __launch_bounds__(TBL_THREADS) k_table(Shape s, int B, int T,
+                                                       const int32_t* __restrict__ cu, Table t) {
+    __shared__ int32_t s_cnt[TBL_THREADS];
+    __shared__ int32_t s_bad;
+    const int tid = threadIdx.x;
+    if (tid == 0) s_bad = 0;
+    __syncthreads();
+    const int N = s.N;
+    const int per = (N + TBL_THREADS - 1) / TBL_THREADS;
+    const int n0 = min(N, tid * per), n1 = min(N, n0 + per);
+    // clamped bounds of this thread's sequences; count their chunks
+    int32_t cnt = 0;
+    int bad = 0;
+    for (int n = n0; n < n1; ++n) {
+        int32_t a, b;
+        if (cu) {
+            int32_t ra = cu[n], rb = cu[n + 1];
+            a = min(max(ra, 0), s.Ttot);
+            b = min(max(rb, a), s.Ttot);
+            if (ra != a || rb != b) bad = 1;
+            if (n == 0 && ra != 0) bad = 1;
+            if (n == N - 1 && rb != s.Ttot) bad = 1;
+        } else {
+            a = n * T;
+            b = a + T;
+        }
+        t.seq_tok0[n] = a;
+        t.seq_len[n] = b - a;
+        cnt += (b - a + BT - 1) / BT;
+    }
+    if (bad) atomicOr(&s_bad, 1);
+    s_cnt[tid] = cnt;
+    __syncthreads();
+    // inclusive scan of the per-thread counts (Hillis-Steele)
+    for (int off = 1; off < TBL_THREADS; off <<= 1) {
+        int32_t x = (tid >= off) ? s_cnt[tid - off] : 0;
+        __syncthreads();
+        s_cnt[tid] += x;
+        __syncthreads();
+    }
+    int32_t c = s_cnt[tid] - cnt;  // exclusive prefix: first chunk slot of n0
+    for (int n = n0; n < n1; ++n) {
+        const int32_t a = t.seq_tok0[n], L = t.seq_len[n];
+        const int32_t nch = (L + BT - 1) / BT;
+        const int32_t c0 = min(c, s.NC);
+        t.seq_chunk0[n] = c0;
+        for (int j = 0; j < nch; ++j) {
+            const int32_t slot = c + j;
+            if (slot < s.NC) {
+                t.chunk_tok0[slot] = a + j * BT;
+                t.chunk_len[slot] = min(BT, L - j * BT);
+            } else {
+                atomicOr(&s_bad, 1);
+            }
+        }
+        c += nch;
+    }
+    const int32_t total = min(s_cnt[TBL_THREADS - 1], s.NC);
+    if (tid == 0) t.seq_chunk0[N] = total;
+    for (int slot = total + tid; slot < s.NC; slot += TBL_THREADS) {
+        t.chunk_tok0[slot] = 0;
+        t.chunk_len[slot] = 0;
+    }
+    __syncthreads();
+    if (tid == 0) t.err[0] = s_bad ? 1 : 0;
+}
+
+}  // namespace
+
+cudaError_t launch_table(const Shape& s, int B, int T, const int32_t* cu, Table t, cudaStream_t st) {
+    k_table<<<1, TBL_THREADS, 0, st>>>(s, B, T, cu, t);
+    return cudaGetLastError();
+}
+
+}  // namespace kda

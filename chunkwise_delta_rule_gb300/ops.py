@@ -1,0 +1,194 @@
+"""PyTorch-facing binding of the C ABI (same names as include/kda.h).
+
+PyTorch provides device memory and the current stream; every step of the
+operator runs in libkda.so's CUDA kernels. Tensors use the layouts of the C
+ABI: q, k [B, T, H, K]; v [B, T, H, V]; beta [B, T, H]; g [B, T, H, K]
+(per-channel) or [B, T, H] (scalar) in fp32; states [N, H, K, V] in fp32.
+"""
+
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import _lib
+
+_IO = {torch.bfloat16: "bf16", torch.float32: "fp32"}
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+@dataclass
+class Problem:
+    """A validated problem description plus the tensors it points to."""
+
+    c: _lib.KdaProblem
+    q: torch.Tensor
+    k: torch.Tensor
+    v: torch.Tensor
+    beta: torch.Tensor
+    g: Optional[torch.Tensor]
+    h0: Optional[torch.Tensor]
+    cu_seqlens: Optional[torch.Tensor]
+    N: int
+
+    @property
+    def state_shape(self):
+        return (self.N, self.c.H, self.c.K, self.c.V)
+
+
+def _need(cond: bool, msg: str):
+    if not cond:
+        raise ValueError(msg)
+
+
+def make_problem(q, k, v, g, beta, *, gate: str, scale: Optional[float] = None,
+                 initial_state: Optional[torch.Tensor] = None,
+                 cu_seqlens: Optional[torch.Tensor] = None, save_policy: int = 0) -> Problem:
+    _need(q.dim() == 4 and k.shape == q.shape, "q and k must be [B, T, H, K]")
+    B, T, H, K = q.shape
+    _need(v.dim() == 4 and v.shape[:3] == q.shape[:3], "v must be [B, T, H, V]")
+    V = v.shape[3]
+    _need(q.dtype in _IO and k.dtype == q.dtype and v.dtype == q.dtype and beta.dtype == q.dtype,
+          "q, k, v, beta must share one dtype (bf16 or fp32)")
+    _need(tuple(beta.shape) == (B, T, H), "beta must be [B, T, H]")
+    for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta)):
+        _need(t.is_cuda and t.is_contiguous(), f"{name} must be a contiguous CUDA tensor")
+    if gate == "none":
+        _need(g is None, "g must be None without a gate")
+    else:
+        _need(g is not None and g.dtype == torch.float32 and g.is_cuda and g.is_contiguous(),
+              "g must be a contiguous fp32 CUDA tensor")
+        want = (B, T, H, K) if gate == "channel" else (B, T, H)
+        _need(tuple(g.shape) == want, f"g must be {list(want)}")
+    N = B
+    if cu_seqlens is not None:
+        _need(cu_seqlens.dtype == torch.int32 and cu_seqlens.is_cuda and cu_seqlens.dim() == 1,
+              "cu_seqlens must be an int32 CUDA vector")
+        N = cu_seqlens.numel() - 1
+    if initial_state is not None:
+        _need(initial_state.dtype == torch.float32 and initial_state.is_contiguous()
+              and tuple(initial_state.shape) == (N, H, K, V), "initial_state must be fp32 [N, H, K, V]")
+    c = _lib.KdaProblem()
+    c.B, c.T, c.H, c.K, c.V = B, T, H, K, V
+    c.N = N if cu_seqlens is not None else 0
+    c.cu_seqlens = None if cu_seqlens is None else cu_seqlens.data_ptr()
+    c.io = _lib.DTYPES[_IO[q.dtype]]
+    c.gate = _lib.GATES[gate]
+    c.scale = float(scale) if scale is not None else 0.0
+    c.q, c.k, c.v, c.beta = q.data_ptr(), k.data_ptr(), v.data_ptr(), beta.data_ptr()
+    c.g = None if g is None else g.data_ptr()
+    c.h0 = None if initial_state is None else initial_state.data_ptr()
+    c.save_policy = int(save_policy)
+    c.schedule = 0
+    return Problem(c, q, k, v, beta, g, initial_state, cu_seqlens, N)
+
+
+def kda_workspace_size(p: Problem, for_backward: bool) -> int:
+    return int(_lib.load().kda_workspace_size(ctypes.byref(p.c), 1 if for_backward else 0))
+
+
+def kda_saved_size(p: Problem) -> int:
+    return int(_lib.load().kda_saved_size(ctypes.byref(p.c)))
+
+
+def kda_last_error() -> str:
+    return _lib.last_error()
+
+
+def _buffer(nbytes: int, device, given: Optional[torch.Tensor]) -> Optional[torch.Tensor]:
+    if nbytes == 0:
+        return given
+    if given is not None and given.numel() * given.element_size() >= nbytes:
+        return given
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def kda_chunk_fwd(p: Problem, *, output_final_state: bool = True, workspace=None, saved=None,
+                  stream=None):
+    """Forward pass. Returns (o, ht or None, saved or None)."""
+    lib = _lib.load()
+    dev = p.q.device
+    o = torch.empty_like(p.v)
+    ht = torch.empty(p.state_shape, dtype=torch.float32, device=dev) if output_final_state else None
+    ws = _buffer(kda_workspace_size(p, False), dev, workspace)
+    sv = None
+    if p.c.save_policy:
+        sv = _buffer(kda_saved_size(p), dev, saved)
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    st = lib.kda_chunk_fwd(ctypes.byref(p.c), _ptr(o), _ptr(ht), _ptr(sv), _ptr(ws), nbytes,
+                           _stream(stream))
+    _lib.check(st, "kda_chunk_fwd")
+    return o, ht, sv
+
+
+def kda_chunk_bwd(p: Problem, do: torch.Tensor, dht: Optional[torch.Tensor] = None, *,
+                  saved=None, workspace=None, stream=None, need_dh0: bool = True):
+    """Backward pass of <do, o> + <dht, ht>. Returns dq, dk, dv, dg, dbeta, dh0."""
+    lib = _lib.load()
+    dev = p.q.device
+    _need(do.shape == p.v.shape and do.dtype == p.v.dtype and do.is_contiguous(), "do must match v")
+    if dht is not None:
+        _need(dht.dtype == torch.float32 and dht.is_contiguous() and tuple(dht.shape) == p.state_shape,
+              "dht must be fp32 [N, H, K, V]")
+    dq = torch.empty_like(p.q)
+    dk = torch.empty_like(p.k)
+    dv = torch.empty_like(p.v)
+    dbeta = torch.empty_like(p.beta)
+    dg = None if p.g is None else torch.empty_like(p.g)
+    dh0 = torch.empty(p.state_shape, dtype=torch.float32, device=dev) if need_dh0 else None
+    ws = _buffer(kda_workspace_size(p, True), dev, workspace)
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    st = lib.kda_chunk_bwd(ctypes.byref(p.c), _ptr(do), _ptr(dht), _ptr(saved), _ptr(dq), _ptr(dk),
+                           _ptr(dv), _ptr(dg), _ptr(dbeta), _ptr(dh0), _ptr(ws), nbytes,
+                           _stream(stream))
+    _lib.check(st, "kda_chunk_bwd")
+    return dq, dk, dv, dg, dbeta, dh0
+
+
+class ChunkKDAFunction(torch.autograd.Function):
+    """Autograd wrapper: forward and backward both run the CUDA library."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, g, beta, initial_state, gate, scale, cu_seqlens, save_policy):
+        p = make_problem(q, k, v, g, beta, gate=gate, scale=scale, initial_state=initial_state,
+                         cu_seqlens=cu_seqlens, save_policy=save_policy)
+        o, ht, sv = kda_chunk_fwd(p)
+        ctx.save_for_backward(q, k, v, g if g is not None else torch.empty(0), beta,
+                              initial_state if initial_state is not None else torch.empty(0),
+                              cu_seqlens if cu_seqlens is not None else torch.empty(0),
+                              sv if sv is not None else torch.empty(0))
+        ctx.meta = (gate, scale, g is not None, initial_state is not None, cu_seqlens is not None,
+                    save_policy)
+        return o, ht
+
+    @staticmethod
+    def backward(ctx, do, dht):
+        q, k, v, g, beta, h0, cu, sv = ctx.saved_tensors
+        gate, scale, has_g, has_h0, has_cu, save_policy = ctx.meta
+        p = make_problem(q, k, v, g if has_g else None, beta, gate=gate, scale=scale,
+                         initial_state=h0 if has_h0 else None, cu_seqlens=cu if has_cu else None,
+                         save_policy=save_policy)
+        do = do.contiguous()
+        dht = None if dht is None else dht.contiguous()
+        dq, dk, dv, dg, dbeta, dh0 = kda_chunk_bwd(p, do, dht, saved=sv if save_policy else None,
+                                                   need_dh0=has_h0)
+        return dq, dk, dv, dg, dbeta, dh0, None, None, None, None
+
+
+def chunk_kda(q, k, v, g, beta, *, gate: str = "channel", scale: Optional[float] = None,
+              initial_state: Optional[torch.Tensor] = None,
+              cu_seqlens: Optional[torch.Tensor] = None, save_policy: int = 0):
+    """Differentiable chunkwise gated delta rule. Returns (o, final_state)."""
+    return ChunkKDAFunction.apply(q, k, v, g, beta, initial_state, gate, scale, cu_seqlens,
+                                  save_policy)

@@ -1,0 +1,149 @@
+/*
+ * kda.h -- C ABI of the GB300 chunkwise gated delta-rule library (libkda.so).
+ *
+ * One operator family: DeltaNet (no decay), Gated DeltaNet (scalar per-head
+ * log-decay) and Kimi Delta Attention (per-key-channel log-decay), forward
+ * and complete backward, over equal-length batches or packed variable-length
+ * sequences.
+ *
+ * Operation (per sequence and head; "Kimi Delta Attention" blog
+ * (mainlymatmul.com), section 4, boxed KDA update, in the key-by-value state
+ * layout printed at the end of that section):
+ *     S~ = diag(exp g_t) S_{t-1};  r_t = beta_t (v_t - S~^T k_t);
+ *     S_t = S~ + k_t r_t^T;        o_t = S_t^T (scale q_t)
+ * computed chunkwise (chunk length 64) as in "ReWY: Faster Backpropagation
+ * for Delta-Rule Attention" (hub.valency.io), sections "The chunk system and
+ * conventional WY backward" and Appendix A; the backward pass is the ReWY
+ * derivative graph of that paper (Algorithm 1, "State and gate composition",
+ * "Matrix intra for vector-gated interactions", "Gram elimination for
+ * scalar-gate gradients", "Complete Reverse Execution and Boundaries").
+ *
+ * Conventions shared by every entry point:
+ *  - All tensor pointers are DEVICE pointers, contiguous, row-major, owned by
+ *    the caller. The library never allocates, frees or synchronises; all work
+ *    is enqueued on the caller's stream and is asynchronous.
+ *  - Token tensors use the packed token axis: [B*T, H, X] (equal lengths:
+ *    sequence b owns tokens b*T .. b*T+T-1; packed: sequence n owns tokens
+ *    cu_seqlens[n] .. cu_seqlens[n+1]-1 and B must be 1).
+ *  - States h0, ht, dht, dh0 are fp32 [N, H, K, V] (key-major), N = B, or the
+ *    number of packed sequences.
+ *  - Arguments are validated before anything is enqueued; on any error
+ *    nothing is written and kda_last_error() describes the problem.
+ *  - Supported widths: K == V, both 64 or 128.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *kda_stream_t;
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, inconsistent fields */
+    KDA_ERR_UNSUPPORTED = 2,   /* valid but not built (e.g. K != V, K = 96) */
+    KDA_ERR_WORKSPACE = 3,     /* workspace or saved buffer too small / misaligned */
+    KDA_ERR_CUDA = 4,          /* a launch or runtime call failed */
+    KDA_ERR_DEVICE_TIMEOUT = 5 /* a bounded device wait gave up (kda_device_status) */
+} kda_status;
+
+/* Element type of q, k, v, beta, o, do, dq, dk, dv, dbeta. */
+typedef enum { KDA_BF16 = 0, KDA_FP32 = 1 } kda_dtype;
+
+/* Log-decay kind ("ReWY" paper, Table 1): none (DeltaNet), scalar per token
+ * and head (Gated DeltaNet, g is [B*T, H]), per key channel (KDA, g is
+ * [B*T, H, K]). */
+typedef enum { KDA_GATE_NONE = 0, KDA_GATE_SCALAR = 1, KDA_GATE_CHANNEL = 2 } kda_gate;
+
+typedef struct {
+    int B, T, H, K, V;          /* batch, tokens per sequence (total tokens when packed),
+                                   heads, key width, value width */
+    int N;                      /* packed sequences (used only when cu_seqlens != NULL) */
+    const int32_t *cu_seqlens;  /* device, N+1 non-decreasing token offsets, first 0,
+                                   last B*T; NULL for equal-length sequences */
+    kda_dtype io;               /* element type of the token tensors */
+    kda_gate gate;
+    float scale;                /* query scale; <= 0 selects K^-1/2 */
+    const void *q, *k;          /* [B*T, H, K] io dtype */
+    const void *v;              /* [B*T, H, V] io dtype */
+    const void *beta;           /* [B*T, H] io dtype */
+    const float *g;             /* natural-log decay, fp32: [B*T, H] (SCALAR) or
+                                   [B*T, H, K] (CHANNEL); NULL iff gate == NONE.
+                                   Values must satisfy -11 < g <= 0: sub-chunk
+                                   factors reach exp(8|g|), which must stay
+                                   below the fp32 maximum. */
+    const float *h0;            /* [N, H, K, V] fp32 or NULL (zero initial state) */
+    int save_policy;            /* 0: backward recomputes the forward (policy R);
+                                   1: forward fills `saved` for the backward (policy A) */
+    int schedule;               /* 0: default; reserved for producer/consumer schedules */
+} kda_problem;
+
+/* Bytes of device workspace kda_chunk_fwd (for_backward = 0) or kda_chunk_bwd
+ * (for_backward = 1) needs for this problem; 0 if the problem is invalid.
+ * Only the size fields, io, gate, cu_seqlens (null or not) and save_policy
+ * are read. The workspace must be 256-byte aligned; its contents need no
+ * initialisation and are scratch after the call. */
+size_t kda_workspace_size(const kda_problem *p, int for_backward);
+
+/* Bytes of the `saved` buffer used by save_policy 1 (0 for policy 0). */
+size_t kda_saved_size(const kda_problem *p);
+
+/* Forward pass. Writes o [B*T, H, V] (io dtype) and, if ht != NULL, the final
+ * state of every sequence [N, H, K, V] fp32. With save_policy 1, `saved`
+ * (kda_saved_size bytes, 256-byte aligned) receives the chunk intermediates
+ * the backward pass reads; it is ignored (may be NULL) under policy 0.
+ * Enqueued on `stream`; returns after validation and launch. */
+kda_status kda_chunk_fwd(const kda_problem *p, void *o, float *ht, void *saved, void *ws,
+                         size_t ws_bytes, kda_stream_t stream);
+
+/* Backward pass of <do, o> + <dht, ht>. Inputs: dout [B*T, H, V] (io dtype),
+ * dht [N, H, K, V] fp32 or NULL (zero). With save_policy 1, `saved` must hold
+ * what kda_chunk_fwd wrote for the same inputs. Outputs: dq, dk [B*T, H, K],
+ * dv [B*T, H, V], dbeta [B*T, H] (io dtype); dg fp32 shaped like g (NULL iff
+ * gate == NONE); dh0 [N, H, K, V] fp32 (may be NULL). dq is the gradient with
+ * respect to the unscaled q; dg is with respect to the natural-log decay. */
+kda_status kda_chunk_bwd(const kda_problem *p, const void *dout, const float *dht,
+                         const void *saved, void *dq, void *dk, void *dv, float *dg,
+                         void *dbeta, float *dh0, void *ws, size_t ws_bytes,
+                         kda_stream_t stream);
+
+/* Synchronises `stream` and reads the device error word a previous call left
+ * in `ws` (bit 0: cu_seqlens inconsistent and clamped). Returns KDA_OK when
+ * the word is clear. For diagnostics; the fast path never calls it. */
+kda_status kda_device_status(const kda_problem *p, const void *ws, size_t ws_bytes,
+                             kda_stream_t stream, int32_t *word);
+
+/* Message for the last non-OK status returned on the calling thread
+ * (thread-local; "" if none). */
+const char *kda_last_error(void);
+
+/* Per-kernel device time of the library's own launches (tracing).
+ * kda_profile_begin() starts recording a pair of CUDA events around every
+ * kernel the library enqueues afterwards (on the stream it is launched on);
+ * kda_profile_end() waits for the recorded events, fills up to max_entries
+ * records (one per kernel name, in first-launch order) and stops recording.
+ * Returns the number of records, or -1 on a CUDA error. Not thread-safe:
+ * profile from one host thread. Recording adds one event pair per launch. */
+typedef struct {
+    char name[40];
+    int launches;
+    double total_ms;
+} kda_kernel_time;
+
+int kda_profile_begin(void);
+int kda_profile_end(kda_kernel_time *out, int max_entries);
+
+/* ABI version of this header (bumped on any incompatible change). */
+int kda_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

@@ -1,0 +1,115 @@
+"""Host-side checks of the C ABI (no GPU needed: no call here reaches CUDA)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from chunkwise_delta_rule_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HDR = os.path.join(ROOT, "include", "kda.h")
+
+
+def declared_functions():
+    text = open(HDR).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = _lib.load()
+    names = declared_functions()
+    assert "kda_chunk_fwd" in names and "kda_chunk_bwd" in names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert lib.kda_abi_version() == 1
+
+
+def _prob(**kw):
+    p = _lib.KdaProblem()
+    p.B, p.T, p.H, p.K, p.V = kw.get("B", 2), kw.get("T", 130), kw.get("H", 3), kw.get("K", 128), kw.get("V", 128)
+    p.N = kw.get("N", 0)
+    p.cu_seqlens = kw.get("cu", None)
+    p.io = kw.get("io", 0)
+    p.gate = kw.get("gate", 2)
+    p.scale = 0.0
+    fake = 0x1000
+    p.q = p.k = p.v = p.beta = fake
+    p.g = fake if p.gate != 0 else None
+    p.h0 = None
+    p.save_policy = kw.get("save", 0)
+    p.schedule = 0
+    return p
+
+
+def _ws(p, bwd):
+    return _lib.load().kda_workspace_size(ctypes.byref(p), bwd)
+
+
+def test_workspace_size_arithmetic():
+    # B=2, T=130 -> 3 chunks per sequence, 6 chunk slots, H=3, D=128
+    p = _prob()
+    NC, H, D, BT = 6, 3, 128, 64
+
+    def up(x):
+        return (x + 255) // 256 * 256
+
+    table = up(4 * NC) * 2 + up(4 * 3) + up(4 * 2) * 2 + up(4)
+    chd = NC * H
+    fcore = up(4 * chd * BT * D) * 4 + up(4 * chd * BT * BT) * 2 + up(4 * chd * D)
+    fextra = up(4 * chd * BT * D) + up(4 * chd * D * D)
+    bwd = up(4 * chd * BT * D) * 4 + up(4 * chd * D * D) + up(4 * chd * BT * BT) * 2 + up(4 * chd * D) + up(4 * chd * BT)
+    assert _ws(p, 0) == table + fcore
+    assert _ws(p, 1) == table + fcore + fextra + bwd
+    pa = _prob(save=1)
+    assert _ws(pa, 0) == table
+    assert _ws(pa, 1) == table + bwd
+    assert _lib.load().kda_saved_size(ctypes.byref(pa)) == fcore + fextra
+    assert _lib.load().kda_saved_size(ctypes.byref(p)) == 0
+    # packed: chunk slots = ceil(T/64) + N
+    pv = _prob(B=1, T=300, N=4, cu=0x2000)
+    NCv = 5 + 4
+    tablev = up(4 * NCv) * 2 + up(4 * 5) + up(4 * 4) * 2 + up(4)
+    chv = NCv * 3
+    assert _ws(pv, 0) == tablev + up(4 * chv * BT * D) * 4 + up(4 * chv * BT * BT) * 2 + up(4 * chv * D)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(K=96, V=96), 2),
+    (dict(K=128, V=64), 2),
+    (dict(B=0), 1),
+    (dict(gate=7), 1),
+    (dict(io=5), 1),
+    (dict(B=2, cu=0x2000, N=3), 1),
+    (dict(save=3), 1),
+])
+def test_invalid_problems_are_rejected_before_launch(kw, status):
+    lib = _lib.load()
+    p = _prob(**kw)
+    st = lib.kda_chunk_fwd(ctypes.byref(p), ctypes.c_void_p(0x3000), None, None, None, 0, None)
+    assert st == status, _lib.last_error()
+    assert _lib.last_error()
+    assert _ws(p, 0) == 0
+
+
+def test_missing_pointers_and_workspace():
+    lib = _lib.load()
+    p = _prob()
+    p.q = None
+    assert lib.kda_chunk_fwd(ctypes.byref(p), ctypes.c_void_p(0x3000), None, None, None, 0, None) == 1
+    p = _prob(gate=0)
+    p.g = 0x1000
+    assert lib.kda_chunk_fwd(ctypes.byref(p), ctypes.c_void_p(0x3000), None, None, None, 0, None) == 1
+    p = _prob()
+    # workspace missing, misaligned, too small
+    assert lib.kda_chunk_fwd(ctypes.byref(p), ctypes.c_void_p(0x3000), None, None, None, 0, None) == 3
+    assert lib.kda_chunk_fwd(ctypes.byref(p), ctypes.c_void_p(0x3000), None, None,
+                             ctypes.c_void_p(0x10010), 1 << 40, None) == 3
+    assert lib.kda_chunk_fwd(ctypes.byref(p), ctypes.c_void_p(0x3000), None, None,
+                             ctypes.c_void_p(0x10000), 100, None) == 3
+    # backward: dg required with a gate
+    z = ctypes.c_void_p(0x3000)
+    st = lib.kda_chunk_bwd(ctypes.byref(p), z, None, None, z, z, z, None, z, None, None, 0, None)
+    assert st == 1 and "dg" in _lib.last_error()

@@ -1,0 +1,247 @@
+"""GPU parity: the CUDA path through the C ABI against the FP64 oracle.
+
+Tolerances (normwise relative error per tensor, all values finite):
+1e-4 for fp32 I/O and 2e-2 for bf16 I/O, for o, ht, dq, dk, dv, dg, dbeta
+and dh0; a reference with near-zero norm uses max-abs <= 1e-6 instead.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from tests.helpers import check_close, np64, run_oracle, run_oracle_pairs
+from workloads import CONFIGS, make_case, make_config_case
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"fp32": 1e-4, "bf16": 2e-2}
+NAMES = ("o", "ht", "dq", "dk", "dv", "dg", "dbeta", "dh0")
+
+
+def gpu_run(case, policy=0, need_bwd=True):
+    import chunkwise_delta_rule_gb300 as kda
+    c = case.to("cuda")
+    p = kda.make_problem(c.q, c.k, c.v, c.g, c.beta, gate=case.gate, scale=case.scale,
+                         initial_state=c.h0, cu_seqlens=c.cu_seqlens, save_policy=policy)
+    o, ht, sv = kda.kda_chunk_fwd(p)
+    out = dict(o=o, ht=ht)
+    if need_bwd:
+        dq, dk, dv, dg, dbeta, dh0 = kda.kda_chunk_bwd(p, c.do, c.dht, saved=sv)
+        out.update(dq=dq, dk=dk, dv=dv, dg=dg, dbeta=dbeta, dh0=dh0)
+    torch.cuda.synchronize()
+    return out
+
+
+def packed_np(case, out):
+    """GPU outputs as float64 arrays on the packed token axis."""
+    BT = case.B * case.T
+    res = {}
+    for k, x in out.items():
+        if x is None:
+            res[k] = None
+            continue
+        a = np64(x)
+        if k in ("ht", "dh0"):
+            res[k] = a
+        elif k in ("dbeta",):
+            res[k] = a.reshape(BT, case.H)
+        elif k == "dg":
+            res[k] = a.reshape((BT, case.H) + tuple(a.shape[3:]))
+        else:
+            res[k] = a.reshape(BT, case.H, -1)
+    return res
+
+
+def compare_full(case, got, ref, tol):
+    errs = {}
+    for name in NAMES:
+        if name not in got:
+            continue
+        if name == "dg" and case.gate == "none":
+            assert got["dg"] is None
+            continue
+        errs[name] = check_close(name, got[name], ref[name], tol)
+    return errs
+
+
+SMALL = [
+    dict(io="fp32", gate="channel", B=2, T=200, H=2, K=64, V=64),
+    dict(io="fp32", gate="scalar", B=2, T=130, H=2, K=64, V=64),
+    dict(io="fp32", gate="none", B=1, T=129, H=3, K=64, V=64),
+    dict(io="fp32", gate="channel", B=1, T=192, H=2, K=128, V=128),
+    dict(io="bf16", gate="channel", B=2, T=150, H=2, K=128, V=128),
+    dict(io="bf16", gate="scalar", B=1, T=257, H=2, K=128, V=128),
+    dict(io="bf16", gate="none", B=2, T=100, H=2, K=128, V=128, h0=False, dht=False),
+    dict(io="bf16", gate="channel", B=1, T=64, H=1, K=64, V=64),
+    dict(io="fp32", gate="channel", B=3, T=1, H=2, K=64, V=64),
+]
+
+
+@pytest.mark.parametrize("kw", SMALL, ids=lambda kw: "{io}-{gate}-B{B}T{T}H{H}K{K}".format(**kw))
+def test_small_cases_match_oracle(kw):
+    case = make_case(seed=17, **kw)
+    got = packed_np(case, gpu_run(case))
+    ref = run_oracle(case)
+    compare_full(case, got, ref, TOL[case.io])
+
+
+@pytest.mark.parametrize("io", ["fp32", "bf16"])
+def test_packed_sequences(io):
+    # one-token, exactly-one-chunk, one-past-a-chunk, two-chunk and ragged sequences
+    case = make_case(io=io, gate="channel", B=1, H=2, K=64, V=64, seed=31,
+                     lengths=[1, 64, 65, 130, 3, 200])
+    got = packed_np(case, gpu_run(case))
+    compare_full(case, got, run_oracle(case), TOL[io])
+
+
+@pytest.mark.parametrize("gate", ["channel", "scalar"])
+def test_strong_decay_takes_the_subchunk_path(gate):
+    """g around -4: the in-chunk gate range exceeds the centering threshold,
+    so the 16-token anchored path runs; it must stay exact in fp32."""
+    case = make_case(io="fp32", gate=gate, B=1, T=200, H=2, K=64, V=64, seed=5, g_shift=-4.0,
+                     g_min=-8.0)
+    g = case.g if gate == "channel" else case.g[..., None]
+    G = torch.cumsum(g.double(), dim=1) / np.log(2.0)
+    assert float((G[:, :64].max(dim=1).values - G[:, :64].min(dim=1).values).max()) > 80
+    got = packed_np(case, gpu_run(case))
+    compare_full(case, got, run_oracle(case), TOL["fp32"])
+
+
+@pytest.mark.parametrize("mode", ["zero_every3", "tiny"])
+def test_zero_and_tiny_beta(mode):
+    case = make_case(io="fp32", gate="channel", B=1, T=130, H=2, K=64, V=64, seed=9, beta_mode=mode)
+    got = packed_np(case, gpu_run(case))
+    compare_full(case, got, run_oracle(case), TOL["fp32"])
+
+
+def test_policy_a_matches_policy_r_bitwise_and_runs_are_deterministic():
+    case = make_case(io="bf16", gate="channel", B=2, T=300, H=2, K=128, V=128, seed=41)
+    r1 = gpu_run(case, policy=0)
+    r2 = gpu_run(case, policy=0)
+    ra = gpu_run(case, policy=1)
+    for name in NAMES:
+        assert torch.equal(r1[name], r2[name]), name
+        assert torch.equal(r1[name], ra[name]), name
+
+
+def test_split_call_chains_through_the_state():
+    import chunkwise_delta_rule_gb300 as kda
+    case = make_case(io="fp32", gate="channel", B=1, T=200, H=2, K=64, V=64, seed=43).to("cuda")
+    full = gpu_run(case)
+    cut = 70
+
+    def part(a, b, h0, dht):
+        sl = lambda x: x[:, a:b].contiguous()  # noqa: E731
+        p = kda.make_problem(sl(case.q), sl(case.k), sl(case.v), sl(case.g), sl(case.beta),
+                             gate="channel", initial_state=h0)
+        o, ht, _ = kda.kda_chunk_fwd(p)
+        return p, o, ht
+
+    pa, oa, hta = part(0, cut, case.h0, None)
+    pb, ob, htb = part(cut, 200, hta, None)
+    gb = kda.kda_chunk_bwd(pb, case.do[:, cut:].contiguous(), case.dht)
+    ga = kda.kda_chunk_bwd(pa, case.do[:, :cut].contiguous(), gb[5])
+    torch.cuda.synchronize()
+    tol = 1e-5
+    assert float((torch.cat([oa, ob], 1) - full["o"]).norm() / full["o"].norm()) < tol
+    assert float((htb - full["ht"]).norm() / full["ht"].norm()) < tol
+    for i, name in enumerate(("dq", "dk", "dv", "dg", "dbeta")):
+        cat = torch.cat([ga[i], gb[i]], 1)
+        assert float((cat - full[name]).norm() / full[name].norm()) < tol, name
+    assert float((ga[5] - full["dh0"]).norm() / full["dh0"].norm()) < tol
+
+
+def test_empty_sequence_passes_states_through():
+    import chunkwise_delta_rule_gb300 as kda
+    case = make_case(io="bf16", gate="channel", B=2, T=0, H=2, K=64, V=64, seed=1).to("cuda")
+    p = kda.make_problem(case.q, case.k, case.v, case.g, case.beta, gate="channel",
+                         initial_state=case.h0)
+    o, ht, _ = kda.kda_chunk_fwd(p)
+    dq, dk, dv, dg, dbeta, dh0 = kda.kda_chunk_bwd(p, case.do, case.dht)
+    torch.cuda.synchronize()
+    assert o.numel() == 0 and torch.equal(ht, case.h0) and torch.equal(dh0, case.dht)
+
+
+def test_autograd_wrapper_matches_direct_calls():
+    import chunkwise_delta_rule_gb300 as kda
+    case = make_case(io="bf16", gate="scalar", B=1, T=140, H=2, K=128, V=128, seed=47).to("cuda")
+    ref = gpu_run(case)
+    q, k, v, g, beta, h0 = (x.clone().requires_grad_(True) for x in
+                            (case.q, case.k, case.v, case.g, case.beta, case.h0))
+    o, ht = kda.chunk_kda(q, k, v, g, beta, gate="scalar", initial_state=h0)
+    loss = (o.float() * case.do.float()).sum() + (ht * case.dht).sum()
+    loss.backward()
+    assert torch.equal(o, ref["o"]) and torch.equal(ht, ref["ht"])
+    for t, name in ((q, "dq"), (k, "dk"), (v, "dv"), (g, "dg"), (beta, "dbeta"), (h0, "dh0")):
+        assert torch.equal(t.grad, ref[name]), name
+
+
+def test_cuda_graph_replay_with_new_inputs():
+    """Capture forward + backward once, replay with different inputs copied
+    into the captured buffers; results equal eager calls on those inputs."""
+    import chunkwise_delta_rule_gb300 as kda
+    a = make_case(io="bf16", gate="channel", B=1, T=200, H=2, K=128, V=128, seed=51).to("cuda")
+    b = make_case(io="bf16", gate="channel", B=1, T=200, H=2, K=128, V=128, seed=52).to("cuda")
+    st = a.to("cuda")
+    p = kda.make_problem(st.q, st.k, st.v, st.g, st.beta, gate="channel", initial_state=st.h0)
+    wf = torch.empty(kda.kda_workspace_size(p, False), dtype=torch.uint8, device="cuda")
+    wb = torch.empty(kda.kda_workspace_size(p, True), dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        kda.kda_chunk_fwd(p, workspace=wf)
+        kda.kda_chunk_bwd(p, st.do, st.dht, workspace=wb)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        outs = kda.kda_chunk_fwd(p, workspace=wf)
+        grads = kda.kda_chunk_bwd(p, st.do, st.dht, workspace=wb)
+    for name in ("q", "k", "v", "g", "beta", "h0", "do", "dht"):
+        getattr(st, name).copy_(getattr(b, name))
+    g.replay()
+    torch.cuda.synchronize()
+    ref = gpu_run(b)
+    assert torch.equal(outs[0], ref["o"]) and torch.equal(outs[1], ref["ht"])
+    for i, name in enumerate(("dq", "dk", "dv", "dg", "dbeta", "dh0")):
+        assert torch.equal(grads[i], ref[name]), name
+
+
+def _sample_pairs(case, n=3):
+    N, H = case.N, case.H
+    pairs = [(0, 0), (N - 1, H - 1), (N // 2, H // 2)]
+    out = []
+    for p in pairs:
+        if p not in out:
+            out.append(p)
+    return out[:n]
+
+
+@pytest.mark.parametrize("idx", [1, 2, 3, 4, 5])
+def test_full_size_configs_on_sampled_heads(idx):
+    """The benchmark workloads at full size, in the launch configuration the
+    benchmark times; the oracle recomputes sampled (sequence, head) pairs
+    one by one and every output must be finite everywhere."""
+    case = make_config_case(idx)
+    out = gpu_run(case)
+    for name, x in out.items():
+        if x is not None:
+            assert bool(torch.isfinite(x.float()).all()), name
+    got = packed_np(case, out)
+    del out
+    pairs = _sample_pairs(case) if idx != 1 else [(n, h) for n in range(case.N) for h in range(case.H)]
+    ref = run_oracle_pairs(case, pairs)
+    ss = case.seq_starts
+    tol = TOL[CONFIGS[idx]["io"]]
+    for name in NAMES:
+        if name == "dg" and case.gate == "none":
+            continue
+        g_parts, r_parts = [], []
+        for i, (n, h) in enumerate(pairs):
+            if name in ("ht", "dh0"):
+                g_parts.append(got[name][n, h])
+            else:
+                g_parts.append(got[name][ss[n]:ss[n + 1], h])
+            r_parts.append(ref[name][i])
+        check_close(f"config{idx}:{name}", np.concatenate([x.ravel() for x in g_parts]),
+                    np.concatenate([x.ravel() for x in r_parts]), tol)
