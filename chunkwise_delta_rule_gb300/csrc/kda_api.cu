@@ -197,6 +197,10 @@ cudaError_t traced(const char* name, cudaStream_t cs, F&& launch) {
 
 }  // namespace
 
+namespace kda {
+void set_last_error(const char* msg) { g_err = msg; }
+}  // namespace kda
+
 extern "C" {
 
 int kda_abi_version(void) { return 1; }

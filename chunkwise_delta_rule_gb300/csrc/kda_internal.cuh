@@ -125,6 +125,9 @@ inline cudaError_t set_smem_once(size_t bytes) {
     return e;
 }
 
+// Sets the message kda_last_error() returns on this host thread.
+void set_last_error(const char* msg);
+
 // --------------------------------------------------------------- launchers
 // Each returns cudaSuccess or the launch error. Defined in the .cu files.
 cudaError_t launch_table(const Shape& s, int B, int T, const int32_t* cu, Table t, cudaStream_t st);

@@ -113,6 +113,29 @@ kda_status kda_chunk_bwd(const kda_problem *p, const void *dout, const float *dh
                          void *dbeta, float *dh0, void *ws, size_t ws_bytes,
                          kda_stream_t stream);
 
+/* Forward pass for callers that cannot allocate device memory: code running
+ * inside an allocator's own hooks, processes whose device memory is fully
+ * reserved up front by an arena they do not control, or latency-critical
+ * paths where an allocation's implicit device synchronisation is not
+ * acceptable. The pages have no counterpart to this entry point; it only
+ * changes where the forward workspace lives.
+ * Same contract as kda_chunk_fwd with save_policy 0, except that the
+ * workspace is a library-owned static device array of
+ * KDA_NOALLOC_SCRATCH_BYTES (32 MiB) that every device loading the library
+ * holds until the process exits. The entry point itself allocates nothing.
+ * - Size limit: problems with kda_workspace_size(p, 0) above the array's size
+ *   (about 200 chunk x head units at K = V = 128) are rejected with
+ *   KDA_ERR_WORKSPACE before anything is enqueued; save_policy must be 0.
+ * - Set-up: the first call on each device, with that device current, looks up
+ *   the array's device address (cudaGetSymbolAddress); make that first call
+ *   before any stream capture on that device.
+ * - Sharing: every call on a device uses the same array, which keeps the last
+ *   call's contents; calls whose GPU work overlaps (other streams, other host
+ *   threads) race on it and must be serialised by the caller. No word of the
+ *   array needs to start at zero: the forward writes all it reads. */
+#define KDA_NOALLOC_SCRATCH_BYTES (32u << 20)
+kda_status kda_chunk_fwd_noalloc(const kda_problem *p, void *o, float *ht, kda_stream_t stream);
+
 /* Synchronises `stream` and reads the device error word a previous call left
  * in `ws` (bit 0: cu_seqlens inconsistent and clamped). Returns KDA_OK when
  * the word is clear. For diagnostics; the fast path never calls it. */
