@@ -57,8 +57,12 @@ kda_status check_dims(const kda_problem* p, Dims& d) {
 }
 
 struct Layout {
-    size_t table = 0, fcore = 0, fextra = 0, bwd = 0;
+    size_t table = 0, fcore = 0, fextra = 0, bwd = 0, ftc = 0;
 };
+
+// The tensor-core path serves bf16 I/O at K = V = 128 (the recompute policy);
+// everything else runs the fp32 CUDA-core kernels.
+bool use_tc_fwd(const kda_problem* p) { return p->io == KDA_BF16 && p->K == 128 && p->save_policy == 0; }
 
 Layout layout(const Dims& d) {
     Layout L;
@@ -71,6 +75,8 @@ Layout layout(const Dims& d) {
     L.fextra = up(4 * chd * BT * D) + up(4 * chd * D * D);
     L.bwd = up(4 * chd * BT * D) * 4 + up(4 * chd * D * D) + up(4 * chd * BT * BT) * 2 +
             up(4 * chd * D) + up(4 * chd * BT);
+    L.ftc = up(2 * chd * BT * D) * 3 + up(2 * chd * BT * BT) + up(4 * chd * BT * D) + up(4 * chd * D) +
+            up(4 * chd);
     return L;
 }
 
@@ -124,6 +130,18 @@ void carve_bwd(Carver& c, const Dims& d, kda::Bwd& b) {
     b.HQ = c.take<float>(4 * chd * BT * BT);
     b.LAMB = c.take<float>(4 * chd * D);
     b.DBW = c.take<float>(4 * chd * BT);
+}
+
+void carve_fwd_tc(Carver& c, const Dims& d, kda::FwdTC& f) {
+    const size_t chd = (size_t)d.NC * d.H, D = d.D, BT = kda::BT;
+    std::memset(&f, 0, sizeof(f));
+    f.W = c.take<__nv_bfloat16>(2 * chd * BT * D);
+    f.KGT = c.take<__nv_bfloat16>(2 * chd * BT * D);
+    f.QG = c.take<__nv_bfloat16>(2 * chd * BT * D);
+    f.AQK = c.take<__nv_bfloat16>(2 * chd * BT * BT);
+    f.U = c.take<float>(4 * chd * BT * D);
+    f.GL = c.take<float>(4 * chd * D);
+    f.WIDE = c.take<int32_t>(4 * chd);
 }
 
 kda::Shape shape_of(const kda_problem* p, const Dims& d) {
@@ -212,7 +230,7 @@ size_t kda_workspace_size(const kda_problem* p, int for_backward) {
     if (check_dims(p, d) != KDA_OK) return 0;
     if (d.Ttot == 0) return 0;
     const Layout L = layout(d);
-    if (!for_backward) return L.table + (p->save_policy ? 0 : L.fcore);
+    if (!for_backward) return L.table + (use_tc_fwd(p) ? L.ftc : (p->save_policy ? 0 : L.fcore));
     return L.table + (p->save_policy ? 0 : L.fcore + L.fextra) + L.bwd;
 }
 
@@ -246,6 +264,20 @@ kda_status kda_chunk_fwd(const kda_problem* p, void* o, float* ht, void* saved, 
     const kda::Shape s = shape_of(p, d);
     Carver cw{static_cast<char*>(ws)};
     kda::Table t = carve_table(cw, d);
+    const int bf16 = p->io == KDA_BF16;
+    cudaError_t e = traced("k_table", cs, [&] { return kda::launch_table(s, p->B, p->T, p->cu_seqlens, t, cs); });
+    if (e != cudaSuccess) return cuda_fail(e, "chunk table");
+    if (use_tc_fwd(p)) {
+        kda::FwdTC f;
+        carve_fwd_tc(cw, d, f);
+        e = traced("k_prep_tc", cs, [&] { return kda::launch_prep_tc(s, (int)p->gate, 0, p->q, p->k, p->v, p->beta, p->g, t, f, cs); });
+        if (e != cudaSuccess) return cuda_fail(e, "prep");
+        e = traced("k_prep_wide", cs, [&] { return kda::launch_prep_wide(s, (int)p->gate, p->q, p->k, p->v, p->beta, p->g, t, f, cs); });
+        if (e != cudaSuccess) return cuda_fail(e, "prep (wide chunks)");
+        e = traced("k_fwd_scan_tc", cs, [&] { return kda::launch_fwd_scan_tc(s, 1, p->h0, t, f, o, ht, cs); });
+        if (e != cudaSuccess) return cuda_fail(e, "forward scan");
+        return KDA_OK;
+    }
     kda::Fwd f;
     if (p->save_policy) {
         Carver cs2{static_cast<char*>(saved)};
@@ -253,9 +285,6 @@ kda_status kda_chunk_fwd(const kda_problem* p, void* o, float* ht, void* saved, 
     } else {
         carve_fwd(cw, d, f, false);
     }
-    const int bf16 = p->io == KDA_BF16;
-    cudaError_t e = traced("k_table", cs, [&] { return kda::launch_table(s, p->B, p->T, p->cu_seqlens, t, cs); });
-    if (e != cudaSuccess) return cuda_fail(e, "chunk table");
     e = traced("k_prep", cs, [&] { return kda::launch_prep(s, bf16, (int)p->gate, p->q, p->k, p->v, p->beta, p->g, t, f, cs); });
     if (e != cudaSuccess) return cuda_fail(e, "prep");
     e = traced("k_fwd_scan", cs, [&] { return kda::launch_fwd_scan(s, bf16, p->save_policy ? 3 : 1, p->h0, t, f, o, ht, cs); });

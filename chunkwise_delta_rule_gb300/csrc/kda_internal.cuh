@@ -54,6 +54,30 @@ struct Bwd {
     float* DBW;   // [NC,H,BT]    <v_i, P_i>
 };
 
+// Chunk intermediates of the tensor-core (bf16 I/O, K = V = 128) path. bf16
+// tiles are stored in the row orders the MMAs read as K-major operands.
+struct FwdTC {
+    __nv_bfloat16* W;     // [NC,H,BT,D]  W = A E, rows = chunk tokens
+    __nv_bfloat16* KGT;   // [NC,H,D,BT]  F^T (keys decayed to the chunk end), rows = keys
+    __nv_bfloat16* QG;    // [NC,H,BT,D]  Q_g
+    __nv_bfloat16* AQK;   // [NC,H,BT,BT] C_q, rows = receiving token i
+    float* U;             // [NC,H,BT,D]  U = A Z
+    float* GL;            // [NC,H,D]     cumulative log2-decay at the last token
+    int32_t* WIDE;        // [NC,H]       1: gate range too wide for one anchor
+    // backward-only copies (null in the forward)
+    __nv_bfloat16* WT;    // [NC,H,D,BT]
+    __nv_bfloat16* KG;    // [NC,H,BT,D]
+    __nv_bfloat16* QGT;   // [NC,H,D,BT]
+    __nv_bfloat16* AQKT;  // [NC,H,BT,BT] C_q^T
+    __nv_bfloat16* AIT;   // [NC,H,BT,BT] A^T
+    __nv_bfloat16* HS;    // [NC,H,D,D]   state entering the chunk, [key][value]
+    __nv_bfloat16* R;     // [NC,H,BT,D]  corrections
+};
+
+// Single-anchor limit of the tensor-core prep (log2 units of the per-feature
+// in-chunk gate range); wider chunks are prepared on CUDA cores.
+constexpr float PREP_RANGE_LOG2 = 80.0f;
+
 struct Shape {
     int H, K, V;
     int N;        // sequences
@@ -139,6 +163,16 @@ cudaError_t launch_prep(const Shape& s, int io_bf16, int gate, const void* q, co
 // mode bit 0: write o; bit 1: write R and SIN for the backward pass.
 cudaError_t launch_fwd_scan(const Shape& s, int io_bf16, int mode, const float* h0, Table t,
                             Fwd f, void* o, float* ht, cudaStream_t st);
+
+// Tensor-core path (bf16 I/O, K = V = 128).
+cudaError_t launch_prep_tc(const Shape& s, int gate, int for_bwd, const void* q, const void* k,
+                           const void* v, const void* beta, const float* g, Table t, FwdTC f,
+                           cudaStream_t st);
+// CUDA-core prep of the chunks flagged WIDE, written in the tensor-core layouts.
+cudaError_t launch_prep_wide(const Shape& s, int gate, const void* q, const void* k, const void* v,
+                             const void* beta, const float* g, Table t, FwdTC ft, cudaStream_t st);
+cudaError_t launch_fwd_scan_tc(const Shape& s, int mode, const float* h0, Table t, FwdTC f, void* o,
+                               float* ht, cudaStream_t st);
 
 cudaError_t launch_bwd_scan(const Shape& s, int io_bf16, const void* dout, const float* dht,
                             Table t, Fwd f, Bwd b, float* dh0, cudaStream_t st);

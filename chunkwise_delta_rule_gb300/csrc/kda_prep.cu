@@ -17,10 +17,12 @@
 namespace kda {
 namespace {
 
-template <typename TI, int D, int GATE>
+// TCOUT: prepare only the chunks the tensor-core prep flagged as too wide for
+// one anchor, and write the tensor-core path's layouts (bf16 tiles).
+template <typename TI, int D, int GATE, bool TCOUT>
 __global__ void __launch_bounds__(NTHREADS, 1)
     k_prep(Shape s, const TI* __restrict__ q, const TI* __restrict__ k, const TI* __restrict__ v,
-           const TI* __restrict__ beta, const float* __restrict__ g, Table t, Fwd f) {
+           const TI* __restrict__ beta, const float* __restrict__ g, Table t, Fwd f, FwdTC ft) {
     constexpr int LD = D + 1;       // padded row stride of [BT x D] tiles
     constexpr int LA = BT + 1;      // padded row stride of [BT x BT] tiles
     extern __shared__ float smem[];
@@ -39,6 +41,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int tok0 = t.chunk_tok0[c];
     const int H = s.H;
     const size_t ch = (size_t)c * H + h;
+    if (TCOUT && ft.WIDE[ch] == 0) return;
 
     // ---- load chunk rows (rows >= n are zero keys/queries and zero decay)
     for (int idx = tid; idx < BT * D; idx += NTHREADS) {
@@ -69,7 +72,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     // ---- a2: Akk and Aqk, one 16-row sub-chunk of receiving rows at a time
     const float scale = s.scale;
-    float* AQK = f.AQK + ch * BT * BT;
+    float* AQK = TCOUT ? nullptr : f.AQK + ch * BT * BT;
     for (int b = 0; b < BT / BC; ++b) {
         const int ra = b * BC + BC / 2;          // anchor row (padding rows repeat G[n-1])
         const int ncol = (b + 1) * BC;           // columns j that can be <= i
@@ -99,7 +102,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (r < BC) {
                     sAkk[i * LA + j] = (j < i && i < n) ? acc[ii][jj] : 0.f;
                 } else {
-                    AQK[i * BT + j] = (j <= i && i < n) ? acc[ii][jj] : 0.f;
+                    const float x = (j <= i && i < n) ? acc[ii][jj] : 0.f;
+                    if (TCOUT) {
+                        ft.AQK[ch * BT * BT + i * BT + j] = __float2bfloat16_rn(x);
+                        if (ft.AQKT) ft.AQKT[ch * BT * BT + j * BT + i] = __float2bfloat16_rn(x);
+                    } else {
+                        AQK[i * BT + j] = x;
+                    }
                 }
             }
         }
@@ -127,17 +136,30 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // ---- a4: Q_g, F (keys to chunk end), G at the last token
     {
         const float* gl = sG + (n - 1) * LD;
-        float* QG = f.QG + ch * BT * D;
-        float* KG = f.KG + ch * BT * D;
         for (int idx = tid; idx < BT * D; idx += NTHREADS) {
             const int r = idx / D, col = idx % D;
             const float gr = sG[r * LD + col];
-            QG[idx] = scale * sQ[r * LD + col] * exp2f(gr);
-            KG[idx] = sK[r * LD + col] * exp2f(gl[col] - gr);
+            const float qg = scale * sQ[r * LD + col] * exp2f(gr);
+            const float kg = sK[r * LD + col] * exp2f(gl[col] - gr);
+            if (TCOUT) {
+                ft.QG[ch * BT * D + idx] = __float2bfloat16_rn(qg);
+                ft.KGT[ch * BT * D + (size_t)col * BT + r] = __float2bfloat16_rn(kg);
+                if (ft.QGT) ft.QGT[ch * BT * D + (size_t)col * BT + r] = __float2bfloat16_rn(qg);
+                if (ft.KG) ft.KG[ch * BT * D + idx] = __float2bfloat16_rn(kg);
+            } else {
+                f.QG[ch * BT * D + idx] = qg;
+                f.KG[ch * BT * D + idx] = kg;
+            }
         }
-        if (tid < D) f.GL[ch * D + tid] = gl[tid];
-        float* AI = f.AINV + ch * BT * BT;
-        for (int idx = tid; idx < BT * BT; idx += NTHREADS) AI[idx] = sAi[(idx / BT) * LA + idx % BT];
+        if (tid < D) (TCOUT ? ft.GL : f.GL)[ch * D + tid] = gl[tid];
+        for (int idx = tid; idx < BT * BT; idx += NTHREADS) {
+            const float a = sAi[(idx / BT) * LA + idx % BT];
+            if (TCOUT) {
+                if (ft.AIT) ft.AIT[ch * BT * BT + (size_t)(idx % BT) * BT + idx / BT] = __float2bfloat16_rn(a);
+            } else {
+                f.AINV[ch * BT * BT + idx] = a;
+            }
+        }
     }
     // E = diag(beta) K exp(G) into sR; beta*v into sQ
     for (int idx = tid; idx < BT * D; idx += NTHREADS) {
@@ -157,18 +179,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         zero(acc);
         tile_gemm<BT, D, 8, TN>(acc, 0, BT, [&](int m, int kk) { return sAi[m * LA + kk]; },
                                 [&](int kk, int nn) { return sR[kk * LD + nn]; });
-        float* W = f.W + ch * BT * D;
 #pragma unroll
         for (int ii = 0; ii < 8; ++ii)
 #pragma unroll
-            for (int jj = 0; jj < TN; ++jj) W[TM8::row(ii) * D + TM8::col(jj)] = acc[ii][jj];
+            for (int jj = 0; jj < TN; ++jj) {
+                const int r = TM8::row(ii), cl = TM8::col(jj);
+                if (TCOUT) {
+                    ft.W[ch * BT * D + r * D + cl] = __float2bfloat16_rn(acc[ii][jj]);
+                    if (ft.WT) ft.WT[ch * BT * D + (size_t)cl * BT + r] = __float2bfloat16_rn(acc[ii][jj]);
+                } else {
+                    f.W[ch * BT * D + r * D + cl] = acc[ii][jj];
+                }
+            }
     }
     {
         float acc[8][TN];
         zero(acc);
         tile_gemm<BT, D, 8, TN>(acc, 0, BT, [&](int m, int kk) { return sAi[m * LA + kk]; },
                                 [&](int kk, int nn) { return sQ[kk * LD + nn]; });
-        float* U = f.U + ch * BT * D;
+        float* U = (TCOUT ? ft.U : f.U) + ch * BT * D;
 #pragma unroll
         for (int ii = 0; ii < 8; ++ii)
 #pragma unroll
@@ -176,30 +205,41 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
 }
 
-template <typename TI, int D, int GATE>
+template <typename TI, int D, int GATE, bool TCOUT>
 cudaError_t run(const Shape& s, const void* q, const void* k, const void* v, const void* beta,
-                const float* g, Table t, Fwd f, cudaStream_t st) {
+                const float* g, Table t, Fwd f, FwdTC ft, cudaStream_t st) {
     constexpr int LD = D + 1, LA = BT + 1;
     constexpr size_t smem = sizeof(float) * (3 * BT * LD + 2 * BC * LD + BT * LD + 2 * BT * LA + BT);
-    auto kern = k_prep<TI, D, GATE>;
-    cudaError_t e = set_smem_once<k_prep<TI, D, GATE>>(smem);
+    auto kern = k_prep<TI, D, GATE, TCOUT>;
+    cudaError_t e = set_smem_once<k_prep<TI, D, GATE, TCOUT>>(smem);
     if (e != cudaSuccess) return e;
     dim3 grid(s.NC, s.H);
-    kern<<<grid, NTHREADS, smem, st>>>(s, (const TI*)q, (const TI*)k, (const TI*)v, (const TI*)beta, g, t, f);
+    kern<<<grid, NTHREADS, smem, st>>>(s, (const TI*)q, (const TI*)k, (const TI*)v, (const TI*)beta, g, t, f, ft);
     return cudaGetLastError();
 }
 
 template <typename TI, int D>
 cudaError_t run_gate(int gate, const Shape& s, const void* q, const void* k, const void* v,
                      const void* beta, const float* g, Table t, Fwd f, cudaStream_t st) {
+    FwdTC none{};
     switch (gate) {
-        case 0: return run<TI, D, 0>(s, q, k, v, beta, g, t, f, st);
-        case 1: return run<TI, D, 1>(s, q, k, v, beta, g, t, f, st);
-        default: return run<TI, D, 2>(s, q, k, v, beta, g, t, f, st);
+        case 0: return run<TI, D, 0, false>(s, q, k, v, beta, g, t, f, none, st);
+        case 1: return run<TI, D, 1, false>(s, q, k, v, beta, g, t, f, none, st);
+        default: return run<TI, D, 2, false>(s, q, k, v, beta, g, t, f, none, st);
     }
 }
 
 }  // namespace
+
+cudaError_t launch_prep_wide(const Shape& s, int gate, const void* q, const void* k, const void* v,
+                             const void* beta, const float* g, Table t, FwdTC ft, cudaStream_t st) {
+    Fwd none{};
+    switch (gate) {
+        case 0: return run<__nv_bfloat16, 128, 0, true>(s, q, k, v, beta, g, t, none, ft, st);
+        case 1: return run<__nv_bfloat16, 128, 1, true>(s, q, k, v, beta, g, t, none, ft, st);
+        default: return run<__nv_bfloat16, 128, 2, true>(s, q, k, v, beta, g, t, none, ft, st);
+    }
+}
 
 cudaError_t launch_prep(const Shape& s, int io_bf16, int gate, const void* q, const void* k,
                         const void* v, const void* beta, const float* g, Table t, Fwd f,

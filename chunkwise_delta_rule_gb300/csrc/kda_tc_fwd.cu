@@ -1,0 +1,609 @@
+// Tensor-core forward path (bf16 I/O, K = V = 128) on tcgen05.
+//
+// k_prep_tc, one CTA per (chunk slot, head) (a1-a4):
+//   G2 = in-chunk cumsum of g / ln 2; one anchor c per feature (the midpoint
+//   of the chunk's range) so that
+//       [Akk ; Aqk] = [beta K 2^(G2-c) ; s Q 2^(G2-c)] (K 2^(c-G2))^T
+//   is a single M = 128, N = 64, K = 128 tf32 MMA ("Kimi Delta Attention"
+//   blog, sections 6.3 and 6.5; "ReWY" paper, centered factors); strict /
+//   inclusive masks on the TMEM read-back; A = (I + Akk)^-1 in fp32 by
+//   forward substitution; W^T = E^T A^T and U^T = Z^T A^T as two M = 128 tf32
+//   MMAs. A chunk whose gate range exceeds 2^80 is left to the CUDA-core prep
+//   (flag WIDE), which anchors per 16-token sub-chunk instead.
+//
+// k_fwd_scan_tc, one CTA per (sequence, head), 128 threads, thread v owns
+// value column v (TMEM lane v). The transposed state S^T (V x K, fp32) stays
+// in TMEM for the whole sequence. Per chunk (a5, a6):
+//       R^T  = U^T - S^T W^T            (MMA, bf16 S^T staged in smem)
+//       O^T  = S^T Q_g^T + R^T C_q^T    (MMAs, output fused)
+//       S^T <- S^T diag(lambda) + R^T F (lambda applied in TMEM, then MMA)
+// ("ReWY" paper, "The chunk system and conventional WY backward"; "Kimi Delta
+// Attention" blog, section 6.4). Operands of chunk c+1 are prefetched with
+// cp.async while chunk c computes.
+#include "kda_internal.cuh"
+#include "tc.cuh"
+
+namespace kda {
+namespace {
+
+using bf16 = __nv_bfloat16;
+constexpr int D = 128;
+
+__device__ __forceinline__ float bfx(const bf16* p) { return __bfloat162float(*p); }
+
+// All threads wait for the barrier phase; the result is made uniform and a
+// timeout is recorded in the device error word (bit 1).
+__device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, int32_t* err) {
+    bool ok = tc::mbar_wait(bar, parity);
+    ok = __syncthreads_and(ok) != 0;
+    if (!ok && threadIdx.x == 0) atomicOr(err, 2);
+    return ok;
+}
+
+// =========================================================== k_prep_tc
+constexpr int PT = 256;
+constexpr int LG = D + 1;  // padded row stride of fp32 [64 x 128] tiles
+constexpr int LA = BT + 1;
+
+template <int GATE, bool BWD>
+__global__ void __launch_bounds__(PT, 1)
+    k_prep_tc(Shape s, const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* __restrict__ v,
+              const bf16* __restrict__ beta, const float* __restrict__ g, Table t, FwdTC f) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                           ~static_cast<uintptr_t>(1023));
+    unsigned char* R1 = base;             // 64 KB operand region (1024-aligned)
+    unsigned char* R2 = R1 + 65536;       // 32 KB operand region
+    float* sG = reinterpret_cast<float*>(R2 + 32768);  // [64][129] cumulative log2-decay
+    float* sK = sG + BT * LG;             // [64][129] keys
+    float* sAkk = sK + BT * LG;           // [64][65]
+    float* sAi = sAkk + BT * LA;          // [64][65]
+    float* sBeta = sAi + BT * LA;         // [64]
+    float* sC = sBeta + BT;               // [128] anchor per feature
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sC + D);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 1);
+
+    const int c = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int n = t.chunk_len[c];
+    if (n <= 0) return;
+    const int tok0 = t.chunk_tok0[c];
+    const int H = s.H;
+    const size_t ch = (size_t)c * H + h;
+    const float scale = s.scale;
+
+    for (int idx = tid; idx < BT * D; idx += PT) {
+        const int r = idx >> 7, col = idx & (D - 1);
+        float kv = 0.f, gv = 0.f;
+        if (r < n) {
+            const size_t off = ((size_t)(tok0 + r) * H + h) * D + col;
+            kv = bfx(k + off);
+            if (GATE == 2) gv = g[off] * LOG2E;
+            if (GATE == 1) gv = g[(size_t)(tok0 + r) * H + h] * LOG2E;
+        }
+        sK[r * LG + col] = kv;
+        sG[r * LG + col] = gv;
+    }
+    if (tid < BT) sBeta[tid] = (tid < n) ? bfx(beta + (size_t)(tok0 + tid) * H + h) : 0.f;
+    if (tid == 0) {
+        tc::mbar_init(bar, 1);
+        tc::fence_mbar_init();
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(tslot, 256);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tb = *tslot;
+
+    // a1: cumsum, range, midpoint anchor
+    int wide_col = 0;
+    if (tid < D) {
+        float acc = 0.f;
+        for (int r = 0; r < BT; ++r) {
+            acc += sG[r * LG + tid];
+            sG[r * LG + tid] = acc;
+        }
+        float hi = sG[tid], lo = sG[tid];
+        for (int r = 1; r < n; ++r) {
+            hi = fmaxf(hi, sG[r * LG + tid]);
+            lo = fminf(lo, sG[r * LG + tid]);
+        }
+        sC[tid] = 0.5f * (hi + lo);
+        wide_col = (hi - lo) > PREP_RANGE_LOG2;
+    }
+    const bool wide = __syncthreads_or(wide_col) != 0;
+    if (tid == 0) f.WIDE[ch] = wide ? 1 : 0;
+    bool ok = true;
+    if (!wide) {
+        // a2 operands (tf32): A rows 0..63 beta_i k_i 2^(G_i-c), rows 64..127 s q_i 2^(G_i-c);
+        // B rows j: k_j 2^(c-G_j). Q_g (and its transpose) are written on the way.
+        bf16* QG = f.QG + ch * BT * D;
+        for (int idx = tid; idx < 2 * BT * 32; idx += PT) {
+            const int r = idx >> 5, cc = idx & 31, i = r & (BT - 1);
+            float4 val;
+            float* pv = reinterpret_cast<float*>(&val);
+            if (r < BT) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int col = 4 * cc + e;
+                    pv[e] = sBeta[i] * sK[i * LG + col] * exp2f(sG[i * LG + col] - sC[col]);
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int col = 4 * cc + e;
+                    const float qv = (i < n) ? bfx(q + ((size_t)(tok0 + i) * H + h) * D + col) : 0.f;
+                    const float gi = sG[i * LG + col];
+                    pv[e] = scale * qv * exp2f(gi - sC[col]);
+                    const float qg = scale * qv * exp2f(gi);
+                    QG[i * D + col] = __float2bfloat16_rn(qg);
+                    if (BWD) f.QGT[ch * BT * D + (size_t)col * BT + i] = __float2bfloat16_rn(qg);
+                }
+            }
+            *reinterpret_cast<float4*>(R1 + tc::sw128_off(2 * BT, r, cc * 16)) = val;
+        }
+        for (int idx = tid; idx < BT * 32; idx += PT) {
+            const int j = idx >> 5, cc = idx & 31;
+            float4 val;
+            float* pv = reinterpret_cast<float*>(&val);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int col = 4 * cc + e;
+                pv[e] = sK[j * LG + col] * exp2f(sC[col] - sG[j * LG + col]);
+            }
+            *reinterpret_cast<float4*>(R2 + tc::sw128_off(BT, j, cc * 16)) = val;
+        }
+        tc::fence_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            tc::fence_after_sync();
+            const uint32_t id = tc::idesc_tf32(128, 64);
+            const uint32_t a0 = tc::smem_u32(R1), b0 = tc::smem_u32(R2);
+#pragma unroll 1
+            for (int st = 0; st < 16; ++st)
+                tc::mma_tf32(tb, tc::sdesc_k(a0, 2 * BT, st), tc::sdesc_k(b0, BT, st), id, st > 0);
+            tc::mma_commit(bar);
+        }
+        ok = wait_all(bar, 0, t.err);
+    }
+    if (!wide && ok) {
+        tc::fence_after_sync();
+        // read back [Akk ; Aqk]: warps w and w+4 share lanes 32(w%4).., split the 64 columns
+        {
+            const int row = 32 * (warp & 3) + lane, cb = (warp >> 2) * 32;
+            float a[32];
+            tc::tmem_ld16(tc::taddr(tb, 32 * (warp & 3), cb), *reinterpret_cast<float(*)[16]>(a));
+            tc::tmem_ld16(tc::taddr(tb, 32 * (warp & 3), cb + 16), *reinterpret_cast<float(*)[16]>(a + 16));
+            tc::tmem_wait_ld();
+            if (row < BT) {
+                const int i = row;
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) {
+                    const int j = cb + jj;
+                    sAkk[i * LA + j] = (j < i && i < n) ? a[jj] : 0.f;
+                }
+            } else {
+                const int i = row - BT;
+                bf16* AQ = f.AQK + ch * BT * BT + (size_t)i * BT + cb;
+#pragma unroll
+                for (int jj = 0; jj < 32; jj += 2) {
+                    const int j = cb + jj;
+                    const float x0 = (j <= i && i < n) ? a[jj] : 0.f;
+                    const float x1 = (j + 1 <= i && i < n) ? a[jj + 1] : 0.f;
+                    *reinterpret_cast<uint32_t*>(AQ + jj) = tc::pack_bf16(x0, x1);
+                    if (BWD) {
+                        f.AQKT[ch * BT * BT + (size_t)j * BT + i] = __float2bfloat16_rn(x0);
+                        f.AQKT[ch * BT * BT + (size_t)(j + 1) * BT + i] = __float2bfloat16_rn(x1);
+                    }
+                }
+            }
+        }
+        tc::fence_before_sync();
+        __syncthreads();
+        // a3: A = (I + Akk)^-1, four lanes per column
+        {
+            const int col = tid >> 2, part = tid & 3;
+            for (int r = part; r < BT; r += 4) sAi[r * LA + col] = (r == col) ? 1.f : 0.f;
+            __syncwarp();
+            for (int i = 1; i < BT; ++i) {
+                float acc = 0.f;
+                if (i > col)
+                    for (int j = col + part; j < i; j += 4) acc = fmaf(sAkk[i * LA + j], sAi[j * LA + col], acc);
+                acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+                acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+                if (part == 0 && i > col) sAi[i * LA + col] = -acc;
+                __syncwarp();
+            }
+        }
+        __syncthreads();
+        // a4 operands (tf32): R1 <- E^T [128 keys][64 tokens], R1+32K <- Z^T [128 values][64 tokens],
+        // R2 <- A [64 rows i][64 cols j] (B operand of W^T = E^T A^T, K = j)
+        for (int idx = tid; idx < D * 16; idx += PT) {
+            const int kr = idx >> 4, cc = idx & 15;
+            float4 val;
+            float* pv = reinterpret_cast<float*>(&val);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int j = 4 * cc + e;
+                pv[e] = sBeta[j] * sK[j * LG + kr] * exp2f(sG[j * LG + kr]);
+            }
+            *reinterpret_cast<float4*>(R1 + tc::sw128_off(D, kr, cc * 16)) = val;
+        }
+        for (int idx = tid; idx < BT * 32; idx += PT) {
+            const int j = idx >> 5, vc = (idx & 31) * 4;
+            float vv[4] = {0.f, 0.f, 0.f, 0.f};
+            if (j < n) {
+                const bf16* vp = v + ((size_t)(tok0 + j) * H + h) * D + vc;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) vv[e] = bfx(vp + e);
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                *reinterpret_cast<float*>(R1 + 32768 + tc::sw128_off(D, vc + e, j * 4)) = sBeta[j] * vv[e];
+        }
+        for (int idx = tid; idx < BT * 16; idx += PT) {
+            const int i = idx >> 4, cc = idx & 15;
+            float4 val;
+            float* pv = reinterpret_cast<float*>(&val);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) pv[e] = sAi[i * LA + 4 * cc + e];
+            *reinterpret_cast<float4*>(R2 + tc::sw128_off(BT, i, cc * 16)) = val;
+        }
+        tc::fence_async_smem();
+        tc::fence_before_sync();
+        __syncthreads();
+        if (tid == 0) {
+            tc::fence_after_sync();
+            const uint32_t id = tc::idesc_tf32(128, 64);
+            const uint32_t a0 = tc::smem_u32(R1), a1 = a0 + 32768, b0 = tc::smem_u32(R2);
+#pragma unroll 1
+            for (int st = 0; st < 8; ++st) tc::mma_tf32(tb + 64, tc::sdesc_k(a0, D, st), tc::sdesc_k(b0, BT, st), id, st > 0);
+#pragma unroll 1
+            for (int st = 0; st < 8; ++st) tc::mma_tf32(tb + 128, tc::sdesc_k(a1, D, st), tc::sdesc_k(b0, BT, st), id, st > 0);
+            tc::mma_commit(bar);
+        }
+        // element-wise outputs while the MMAs run
+        {
+            bf16* KGT = f.KGT + ch * D * BT;
+            for (int idx = tid; idx < D * BT; idx += PT) {
+                const int kr = idx >> 6, i = idx & (BT - 1);
+                const float gl = sG[(n - 1) * LG + kr];
+                KGT[idx] = __float2bfloat16_rn(sK[i * LG + kr] * exp2f(gl - sG[i * LG + kr]));
+            }
+            if (BWD) {
+                bf16* KG = f.KG + ch * BT * D;
+                for (int idx = tid; idx < BT * D; idx += PT) {
+                    const int i = idx >> 7, kr = idx & (D - 1);
+                    const float gl = sG[(n - 1) * LG + kr];
+                    KG[idx] = __float2bfloat16_rn(sK[i * LG + kr] * exp2f(gl - sG[i * LG + kr]));
+                }
+                bf16* AIT = f.AIT + ch * BT * BT;
+                for (int idx = tid; idx < BT * BT; idx += PT) {
+                    const int j = idx >> 6, i = idx & (BT - 1);
+                    AIT[idx] = __float2bfloat16_rn(sAi[i * LA + j]);
+                }
+            }
+            if (tid < D) f.GL[ch * D + tid] = sG[(n - 1) * LG + tid];
+        }
+        ok = wait_all(bar, 1, t.err);
+        if (ok) {
+            tc::fence_after_sync();
+            const int row = 32 * (warp & 3) + lane;
+            if (warp < 4) {
+                // W^T row = key `row`: write W[i][row] and, for the backward, W^T[row][i]
+                bf16* W = f.W + ch * BT * D;
+#pragma unroll 1
+                for (int cb = 0; cb < BT; cb += 16) {
+                    float a[16];
+                    tc::tmem_ld16(tc::taddr(tb + 64, 32 * warp, cb), a);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) W[(size_t)(cb + jj) * D + row] = __float2bfloat16_rn(a[jj]);
+                    if (BWD) {
+                        uint4 pk[2];
+                        uint32_t* pw = reinterpret_cast<uint32_t*>(pk);
+#pragma unroll
+                        for (int jj = 0; jj < 8; ++jj) pw[jj] = tc::pack_bf16(a[2 * jj], a[2 * jj + 1]);
+                        uint4* dst = reinterpret_cast<uint4*>(f.WT + ch * D * BT + (size_t)row * BT + cb);
+                        dst[0] = pk[0];
+                        dst[1] = pk[1];
+                    }
+                }
+            } else {
+                float* U = f.U + ch * BT * D;
+#pragma unroll 1
+                for (int cb = 0; cb < BT; cb += 16) {
+                    float a[16];
+                    tc::tmem_ld16(tc::taddr(tb + 128, 32 * (warp & 3), cb), a);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) U[(size_t)(cb + jj) * D + row] = a[jj];
+                }
+            }
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tb, 256);
+}
+
+// ======================================================= k_fwd_scan_tc
+constexpr int ST = 128;  // threads: one per value column / TMEM lane
+
+// Shared-memory map (bytes from the 1024-aligned base).
+constexpr int OFF_AS = 0;                    // S^T bf16 [128][128]   32 KB
+constexpr int OFF_AR = OFF_AS + 32768;       // R^T bf16 [128][64]    16 KB
+constexpr int OFF_STAGE = OFF_AR + 16384;    // two stages
+constexpr int STG_W = 0;                     // W   [64][128]  16 KB
+constexpr int STG_KG = 16384;                // F^T [128][64]  16 KB
+constexpr int STG_QG = 32768;                // Q_g [64][128]  16 KB
+constexpr int STG_AQ = 49152;                // C_q [64][64]    8 KB
+constexpr int STG_BYTES = 57344;
+constexpr int OFF_BAR = OFF_STAGE + 2 * STG_BYTES;
+constexpr int SCAN_SMEM = OFF_BAR + 64 + 1024;
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// Copies a row-major bf16 [R][C] global tile into a K-major SW128 smem tile.
+template <int R, int C>
+__device__ __forceinline__ void load_tile(uint32_t sbase, const bf16* src, int tid) {
+    constexpr int CPR = C * 2 / 16;  // 16-byte chunks per row
+    for (int idx = tid; idx < R * CPR; idx += ST) {
+        const int r = idx / CPR, cc = idx % CPR;
+        cp_async16(sbase + tc::sw128_off(R, r, cc * 16), src + (size_t)r * C + cc * 8);
+    }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(ST, 1)
+    k_fwd_scan_tc(Shape s, const float* __restrict__ h0, Table t, FwdTC f, bf16* __restrict__ o,
+                  float* __restrict__ ht) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                           ~static_cast<uintptr_t>(1023));
+    uint64_t* bar = reinterpret_cast<uint64_t*>(base + OFF_BAR);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 2);
+    const uint32_t sb = tc::smem_u32(base);
+    const int nseq = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5;
+    const int H = s.H;
+    const int vcol = tid;  // TMEM lane and value column of this thread
+    const int c0 = t.seq_chunk0[nseq], c1 = t.seq_chunk0[nseq + 1];
+
+    if (tid == 0) {
+        tc::mbar_init(&bar[0], 1);
+        tc::mbar_init(&bar[1], 1);
+        tc::fence_mbar_init();
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(tslot, 256);
+        tc::tmem_relinquish();
+    }
+    // prefetch the first chunk's operands
+    if (c0 < c1) {
+        const size_t ch = (size_t)c0 * H + h;
+        const uint32_t stg = sb + OFF_STAGE;
+        load_tile<BT, D>(stg + STG_W, f.W + ch * BT * D, tid);
+        load_tile<D, BT>(stg + STG_KG, f.KGT + ch * D * BT, tid);
+        if (MODE & 1) {
+            load_tile<BT, D>(stg + STG_QG, f.QG + ch * BT * D, tid);
+            load_tile<BT, BT>(stg + STG_AQ, f.AQK + ch * BT * BT, tid);
+        }
+        cp_async_commit();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tb = *tslot;
+    const uint32_t tl = tc::taddr(tb, 32 * warp, 0);  // this warp's lane quarter
+    const size_t st_off = ((size_t)nseq * H + h) * D * D;
+
+    // S^T <- h0^T (thread v holds row v: h0[k][v] for all k)
+#pragma unroll 1
+    for (int cb = 0; cb < D; cb += 16) {
+        float a[16];
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) a[jj] = h0 ? h0[st_off + (size_t)(cb + jj) * D + vcol] : 0.f;
+        tc::tmem_st16(tl + cb, a);
+    }
+    tc::tmem_wait_st();
+
+    uint32_t ph0 = 0, ph1 = 0;
+    bool ok = true;
+    for (int c = c0; c < c1 && ok; ++c) {
+        const int it = c - c0, stage = it & 1;
+        const size_t ch = (size_t)c * H + h;
+        const int len = t.chunk_len[c], tok0 = t.chunk_tok0[c];
+        const uint32_t stg = sb + OFF_STAGE + stage * STG_BYTES;
+        // 1. S^T -> bf16 operand (and the saved state), then S^T <- S^T diag(lambda)
+        const float* GL = f.GL + ch * D;
+#pragma unroll 1
+        for (int cb = 0; cb < D; cb += 16) {
+            float a[16];
+            tc::tmem_ld16(tl + cb, a);
+            tc::tmem_wait_ld();
+            uint4 pk[2];
+            uint32_t* pw = reinterpret_cast<uint32_t*>(pk);
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) pw[jj] = tc::pack_bf16(a[2 * jj], a[2 * jj + 1]);
+            *reinterpret_cast<uint4*>(base + OFF_AS + tc::sw128_off(D, vcol, cb * 2)) = pk[0];
+            *reinterpret_cast<uint4*>(base + OFF_AS + tc::sw128_off(D, vcol, cb * 2 + 16)) = pk[1];
+            if (MODE & 2) {
+                bf16* HS = f.HS + ch * D * D;
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) HS[(size_t)(cb + jj) * D + vcol] = __float2bfloat16_rn(a[jj]);
+            }
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) a[jj] *= exp2f(__ldg(GL + cb + jj));
+            tc::tmem_st16(tl + cb, a);
+        }
+        tc::tmem_wait_st();
+        // 2. U column of this thread
+        float u[BT];
+        const float* U = f.U + ch * BT * D;
+#pragma unroll
+        for (int i = 0; i < BT; ++i) u[i] = U[(size_t)i * D + vcol];
+        cp_async_wait_all();
+        tc::fence_async_smem();
+        tc::fence_before_sync();
+        __syncthreads();
+        // 3. D1 = S^T W^T ; O^T = S^T Q_g^T
+        if (tid == 0) {
+            tc::fence_after_sync();
+            const uint32_t id = tc::idesc_bf16(128, 64);
+            const uint32_t aS = sb + OFF_AS;
+#pragma unroll 1
+            for (int ks = 0; ks < 8; ++ks)
+                tc::mma_bf16(tb + 128, tc::sdesc_k(aS, D, ks), tc::sdesc_k(stg + STG_W, BT, ks), id, ks > 0);
+            if (MODE & 1) {
+#pragma unroll 1
+                for (int ks = 0; ks < 8; ++ks)
+                    tc::mma_bf16(tb + 192, tc::sdesc_k(aS, D, ks), tc::sdesc_k(stg + STG_QG, BT, ks), id, ks > 0);
+            }
+            tc::mma_commit(&bar[0]);
+        }
+        // prefetch chunk c+1 into the other stage (its previous MMAs have completed)
+        if (c + 1 < c1) {
+            const size_t ch1 = (size_t)(c + 1) * H + h;
+            const uint32_t stn = sb + OFF_STAGE + (stage ^ 1) * STG_BYTES;
+            load_tile<BT, D>(stn + STG_W, f.W + ch1 * BT * D, tid);
+            load_tile<D, BT>(stn + STG_KG, f.KGT + ch1 * D * BT, tid);
+            if (MODE & 1) {
+                load_tile<BT, D>(stn + STG_QG, f.QG + ch1 * BT * D, tid);
+                load_tile<BT, BT>(stn + STG_AQ, f.AQK + ch1 * BT * BT, tid);
+            }
+            cp_async_commit();
+        }
+        ok = wait_all(&bar[0], ph0, t.err);
+        ph0 ^= 1;
+        if (!ok) break;
+        tc::fence_after_sync();
+        // 4. R^T = U^T - D1 (bf16 operand; saved for the backward)
+#pragma unroll
+        for (int cb = 0; cb < BT; cb += 16) {
+            float a[16];
+            tc::tmem_ld16(tl + 128 + cb, a);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) a[jj] = u[cb + jj] - a[jj];
+            uint4 pk[2];
+            uint32_t* pw = reinterpret_cast<uint32_t*>(pk);
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) pw[jj] = tc::pack_bf16(a[2 * jj], a[2 * jj + 1]);
+            *reinterpret_cast<uint4*>(base + OFF_AR + tc::sw128_off(D, vcol, cb * 2)) = pk[0];
+            *reinterpret_cast<uint4*>(base + OFF_AR + tc::sw128_off(D, vcol, cb * 2 + 16)) = pk[1];
+            if (MODE & 2) {
+                bf16* Rg = f.R + ch * BT * D;
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) Rg[(size_t)(cb + jj) * D + vcol] = __float2bfloat16_rn(a[jj]);
+            }
+        }
+        tc::fence_async_smem();
+        tc::fence_before_sync();
+        __syncthreads();
+        // 5. S^T += R^T F ; O^T += R^T C_q^T
+        if (tid == 0) {
+            tc::fence_after_sync();
+            const uint32_t aR = sb + OFF_AR;
+#pragma unroll 1
+            for (int ks = 0; ks < 4; ++ks)
+                tc::mma_bf16(tb, tc::sdesc_k(aR, D, ks), tc::sdesc_k(stg + STG_KG, D, ks), tc::idesc_bf16(128, 128), 1);
+            if (MODE & 1) {
+#pragma unroll 1
+                for (int ks = 0; ks < 4; ++ks)
+                    tc::mma_bf16(tb + 192, tc::sdesc_k(aR, D, ks), tc::sdesc_k(stg + STG_AQ, BT, ks), tc::idesc_bf16(128, 64), 1);
+            }
+            tc::mma_commit(&bar[1]);
+        }
+        ok = wait_all(&bar[1], ph1, t.err);
+        ph1 ^= 1;
+        if (!ok) break;
+        tc::fence_after_sync();
+        // 6. output rows of this value column
+        if (MODE & 1) {
+#pragma unroll 1
+            for (int cb = 0; cb < BT; cb += 16) {
+                float a[16];
+                tc::tmem_ld16(tl + 192 + cb, a);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj)
+                    if (cb + jj < len) o[((size_t)(tok0 + cb + jj) * H + h) * D + vcol] = __float2bfloat16_rn(a[jj]);
+            }
+        }
+        tc::fence_before_sync();
+        __syncthreads();
+    }
+    if (ok && ht) {
+        tc::fence_after_sync();
+#pragma unroll 1
+        for (int cb = 0; cb < D; cb += 16) {
+            float a[16];
+            tc::tmem_ld16(tl + cb, a);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) ht[st_off + (size_t)(cb + jj) * D + vcol] = a[jj];
+        }
+    }
+    cp_async_wait_all();
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tb, 256);
+}
+
+constexpr size_t PREP_SMEM = 65536 + 32768 + sizeof(float) * (2 * BT * LG + 2 * BT * LA + BT + D) + 64 + 1024;
+
+template <int GATE, bool BWD>
+cudaError_t run_prep(const Shape& s, const void* q, const void* k, const void* v, const void* beta,
+                     const float* g, Table t, FwdTC f, cudaStream_t st) {
+    cudaError_t e = set_smem_once<k_prep_tc<GATE, BWD>>(PREP_SMEM);
+    if (e != cudaSuccess) return e;
+    dim3 grid(s.NC, s.H);
+    k_prep_tc<GATE, BWD><<<grid, PT, PREP_SMEM, st>>>(s, (const bf16*)q, (const bf16*)k, (const bf16*)v,
+                                                      (const bf16*)beta, g, t, f);
+    return cudaGetLastError();
+}
+
+template <int MODE>
+cudaError_t run_scan(const Shape& s, const float* h0, Table t, FwdTC f, void* o, float* ht, cudaStream_t st) {
+    cudaError_t e = set_smem_once<k_fwd_scan_tc<MODE>>(SCAN_SMEM);
+    if (e != cudaSuccess) return e;
+    dim3 grid(s.N, s.H);
+    k_fwd_scan_tc<MODE><<<grid, ST, SCAN_SMEM, st>>>(s, h0, t, f, (bf16*)o, ht);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prep_tc(const Shape& s, int gate, int for_bwd, const void* q, const void* k,
+                           const void* v, const void* beta, const float* g, Table t, FwdTC f,
+                           cudaStream_t st) {
+    if (for_bwd) {
+        switch (gate) {
+            case 0: return run_prep<0, true>(s, q, k, v, beta, g, t, f, st);
+            case 1: return run_prep<1, true>(s, q, k, v, beta, g, t, f, st);
+            default: return run_prep<2, true>(s, q, k, v, beta, g, t, f, st);
+        }
+    }
+    switch (gate) {
+        case 0: return run_prep<0, false>(s, q, k, v, beta, g, t, f, st);
+        case 1: return run_prep<1, false>(s, q, k, v, beta, g, t, f, st);
+        default: return run_prep<2, false>(s, q, k, v, beta, g, t, f, st);
+    }
+}
+
+cudaError_t launch_fwd_scan_tc(const Shape& s, int mode, const float* h0, Table t, FwdTC f, void* o,
+                               float* ht, cudaStream_t st) {
+    switch (mode) {
+        case 1: return run_scan<1>(s, h0, t, f, o, ht, st);
+        case 2: return run_scan<2>(s, h0, t, f, o, ht, st);
+        default: return run_scan<3>(s, h0, t, f, o, ht, st);
+    }
+}
+
+}  // namespace kda

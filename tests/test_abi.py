@@ -49,8 +49,9 @@ def _ws(p, bwd):
 
 
 def test_workspace_size_arithmetic():
-    # B=2, T=130 -> 3 chunks per sequence, 6 chunk slots, H=3, D=128
-    p = _prob()
+    # B=2, T=130 -> 3 chunks per sequence, 6 chunk slots, H=3, D=128; fp32 I/O
+    # runs the CUDA-core kernels, bf16 I/O at D = 128 the tensor-core forward
+    p = _prob(io=1)
     NC, H, D, BT = 6, 3, 128, 64
 
     def up(x):
@@ -63,13 +64,16 @@ def test_workspace_size_arithmetic():
     bwd = up(4 * chd * BT * D) * 4 + up(4 * chd * D * D) + up(4 * chd * BT * BT) * 2 + up(4 * chd * D) + up(4 * chd * BT)
     assert _ws(p, 0) == table + fcore
     assert _ws(p, 1) == table + fcore + fextra + bwd
+    ptc = _prob(io=0)
+    ftc = up(2 * chd * BT * D) * 3 + up(2 * chd * BT * BT) + up(4 * chd * BT * D) + up(4 * chd * D) + up(4 * chd)
+    assert _ws(ptc, 0) == table + ftc
     pa = _prob(save=1)
     assert _ws(pa, 0) == table
     assert _ws(pa, 1) == table + bwd
     assert _lib.load().kda_saved_size(ctypes.byref(pa)) == fcore + fextra
     assert _lib.load().kda_saved_size(ctypes.byref(p)) == 0
     # packed: chunk slots = ceil(T/64) + N
-    pv = _prob(B=1, T=300, N=4, cu=0x2000)
+    pv = _prob(B=1, T=300, N=4, cu=0x2000, io=1)
     NCv = 5 + 4
     tablev = up(4 * NCv) * 2 + up(4 * 5) + up(4 * 4) * 2 + up(4)
     chv = NCv * 3

@@ -94,17 +94,32 @@ def test_packed_sequences(io):
     compare_full(case, got, run_oracle(case), TOL[io])
 
 
+@pytest.mark.parametrize("io,D", [("fp32", 64), ("bf16", 128)])
 @pytest.mark.parametrize("gate", ["channel", "scalar"])
-def test_strong_decay_takes_the_subchunk_path(gate):
-    """g around -4: the in-chunk gate range exceeds the centering threshold,
-    so the 16-token anchored path runs; it must stay exact in fp32."""
-    case = make_case(io="fp32", gate=gate, B=1, T=200, H=2, K=64, V=64, seed=5, g_shift=-4.0,
+def test_strong_decay_takes_the_subchunk_path(gate, io, D):
+    """g around -4: the in-chunk gate range exceeds the single-anchor and
+    centering thresholds, so the 16-token anchored paths run (the CUDA-core
+    prep of wide chunks on the tensor-core path); they must stay within the
+    I/O dtype's tolerance."""
+    case = make_case(io=io, gate=gate, B=1, T=200, H=2, K=D, V=D, seed=5, g_shift=-4.0,
                      g_min=-8.0)
     g = case.g if gate == "channel" else case.g[..., None]
     G = torch.cumsum(g.double(), dim=1) / np.log(2.0)
     assert float((G[:, :64].max(dim=1).values - G[:, :64].min(dim=1).values).max()) > 80
     got = packed_np(case, gpu_run(case))
-    compare_full(case, got, run_oracle(case), TOL["fp32"])
+    compare_full(case, got, run_oracle(case), TOL[io])
+
+
+def test_mixed_wide_and_narrow_chunks():
+    """Packed sequences where some chunks have strong decay and others mild:
+    the tensor-core prep and the wide-chunk prep share one launch sequence."""
+    case = make_case(io="bf16", gate="channel", B=1, H=2, K=128, V=128, seed=8,
+                     lengths=[64, 150, 70])
+    g = case.g.clone()
+    g[0, 64:214] = torch.clamp(g[0, 64:214] - 4.0, min=-8.0)   # the middle sequence decays strongly
+    case.g = g
+    got = packed_np(case, gpu_run(case))
+    compare_full(case, got, run_oracle(case), TOL["bf16"])
 
 
 @pytest.mark.parametrize("mode", ["zero_every3", "tiny"])
@@ -114,14 +129,17 @@ def test_zero_and_tiny_beta(mode):
     compare_full(case, got, run_oracle(case), TOL["fp32"])
 
 
-def test_policy_a_matches_policy_r_bitwise_and_runs_are_deterministic():
-    case = make_case(io="bf16", gate="channel", B=2, T=300, H=2, K=128, V=128, seed=41)
+@pytest.mark.parametrize("io,D", [("fp32", 64), ("bf16", 128)])
+def test_policies_agree_and_runs_are_deterministic(io, D):
+    """Repeated runs are bitwise identical (no atomics); the save-intermediates
+    policy agrees with the recompute policy within the I/O tolerance."""
+    case = make_case(io=io, gate="channel", B=2, T=300, H=2, K=D, V=D, seed=41)
     r1 = gpu_run(case, policy=0)
     r2 = gpu_run(case, policy=0)
     ra = gpu_run(case, policy=1)
     for name in NAMES:
         assert torch.equal(r1[name], r2[name]), name
-        assert torch.equal(r1[name], ra[name]), name
+        check_close(name, np64(ra[name]), np64(r1[name]), TOL[io])
 
 
 def test_split_call_chains_through_the_state():
