@@ -57,12 +57,13 @@ kda_status check_dims(const kda_problem* p, Dims& d) {
 }
 
 struct Layout {
-    size_t table = 0, fcore = 0, fextra = 0, bwd = 0, ftc = 0;
+    size_t table = 0, fcore = 0, fextra = 0, bwd = 0;   // CUDA-core path
+    size_t ftc = 0, ftc_b = 0, btc = 0, wscr = 0;       // tensor-core path
 };
 
-// The tensor-core path serves bf16 I/O at K = V = 128 (the recompute policy);
-// everything else runs the fp32 CUDA-core kernels.
-bool use_tc_fwd(const kda_problem* p) { return p->io == KDA_BF16 && p->K == 128 && p->save_policy == 0; }
+// The tensor-core path serves bf16 I/O at K = V = 128; everything else runs
+// the fp32 CUDA-core kernels.
+bool use_tc(const kda_problem* p) { return p->io == KDA_BF16 && p->K == 128; }
 
 Layout layout(const Dims& d) {
     Layout L;
@@ -77,6 +78,9 @@ Layout layout(const Dims& d) {
             up(4 * chd * D) + up(4 * chd * BT);
     L.ftc = up(2 * chd * BT * D) * 3 + up(2 * chd * BT * BT) + up(4 * chd * BT * D) + up(4 * chd * D) +
             up(4 * chd);
+    L.ftc_b = up(2 * chd * BT * D) * 3 + up(2 * chd * BT * BT) * 2 + up(2 * chd * D * D) + up(2 * chd * BT * D);
+    L.btc = up(2 * chd * D * D) + up(2 * chd * BT * D);
+    L.wscr = up(4 * chd * BT * D) * 3 + up(4 * chd * BT * BT) * 2 + up(4 * chd * D) + up(4 * chd * BT);
     return L;
 }
 
@@ -132,7 +136,7 @@ void carve_bwd(Carver& c, const Dims& d, kda::Bwd& b) {
     b.DBW = c.take<float>(4 * chd * BT);
 }
 
-void carve_fwd_tc(Carver& c, const Dims& d, kda::FwdTC& f) {
+void carve_fwd_tc(Carver& c, const Dims& d, kda::FwdTC& f, bool bwd_arrays) {
     const size_t chd = (size_t)d.NC * d.H, D = d.D, BT = kda::BT;
     std::memset(&f, 0, sizeof(f));
     f.W = c.take<__nv_bfloat16>(2 * chd * BT * D);
@@ -142,6 +146,29 @@ void carve_fwd_tc(Carver& c, const Dims& d, kda::FwdTC& f) {
     f.U = c.take<float>(4 * chd * BT * D);
     f.GL = c.take<float>(4 * chd * D);
     f.WIDE = c.take<int32_t>(4 * chd);
+    if (bwd_arrays) {
+        f.WT = c.take<__nv_bfloat16>(2 * chd * BT * D);
+        f.KG = c.take<__nv_bfloat16>(2 * chd * BT * D);
+        f.QGT = c.take<__nv_bfloat16>(2 * chd * BT * D);
+        f.AQKT = c.take<__nv_bfloat16>(2 * chd * BT * BT);
+        f.AIT = c.take<__nv_bfloat16>(2 * chd * BT * BT);
+        f.HS = c.take<__nv_bfloat16>(2 * chd * D * D);
+        f.R = c.take<__nv_bfloat16>(2 * chd * BT * D);
+    }
+}
+
+void carve_bwd_tc(Carver& c, const Dims& d, kda::BwdTC& b, kda::Bwd& scr) {
+    const size_t chd = (size_t)d.NC * d.H, D = d.D, BT = kda::BT;
+    b.SBP = c.take<__nv_bfloat16>(2 * chd * D * D);
+    b.P = c.take<__nv_bfloat16>(2 * chd * BT * D);
+    std::memset(&scr, 0, sizeof(scr));
+    scr.QS = c.take<float>(4 * chd * BT * D);
+    scr.PS = c.take<float>(4 * chd * BT * D);
+    scr.FB = c.take<float>(4 * chd * BT * D);
+    scr.DM = c.take<float>(4 * chd * BT * BT);
+    scr.HQ = c.take<float>(4 * chd * BT * BT);
+    scr.LAMB = c.take<float>(4 * chd * D);
+    scr.DBW = c.take<float>(4 * chd * BT);
 }
 
 kda::Shape shape_of(const kda_problem* p, const Dims& d) {
@@ -230,7 +257,11 @@ size_t kda_workspace_size(const kda_problem* p, int for_backward) {
     if (check_dims(p, d) != KDA_OK) return 0;
     if (d.Ttot == 0) return 0;
     const Layout L = layout(d);
-    if (!for_backward) return L.table + (use_tc_fwd(p) ? L.ftc : (p->save_policy ? 0 : L.fcore));
+    if (use_tc(p)) {
+        if (!for_backward) return L.table + (p->save_policy ? 0 : L.ftc);
+        return L.table + (p->save_policy ? 0 : L.ftc + L.ftc_b) + L.btc + L.wscr;
+    }
+    if (!for_backward) return L.table + (p->save_policy ? 0 : L.fcore);
     return L.table + (p->save_policy ? 0 : L.fcore + L.fextra) + L.bwd;
 }
 
@@ -239,7 +270,7 @@ size_t kda_saved_size(const kda_problem* p) {
     if (check_dims(p, d) != KDA_OK) return 0;
     if (!p->save_policy || d.Ttot == 0) return 0;
     const Layout L = layout(d);
-    return L.fcore + L.fextra;
+    return use_tc(p) ? L.ftc + L.ftc_b : L.fcore + L.fextra;
 }
 
 kda_status kda_chunk_fwd(const kda_problem* p, void* o, float* ht, void* saved, void* ws,
@@ -267,14 +298,20 @@ kda_status kda_chunk_fwd(const kda_problem* p, void* o, float* ht, void* saved, 
     const int bf16 = p->io == KDA_BF16;
     cudaError_t e = traced("k_table", cs, [&] { return kda::launch_table(s, p->B, p->T, p->cu_seqlens, t, cs); });
     if (e != cudaSuccess) return cuda_fail(e, "chunk table");
-    if (use_tc_fwd(p)) {
+    if (use_tc(p)) {
         kda::FwdTC f;
-        carve_fwd_tc(cw, d, f);
-        e = traced("k_prep_tc", cs, [&] { return kda::launch_prep_tc(s, (int)p->gate, 0, p->q, p->k, p->v, p->beta, p->g, t, f, cs); });
+        const bool save = p->save_policy != 0;
+        if (save) {
+            Carver cs2{static_cast<char*>(saved)};
+            carve_fwd_tc(cs2, d, f, true);
+        } else {
+            carve_fwd_tc(cw, d, f, false);
+        }
+        e = traced("k_prep_tc", cs, [&] { return kda::launch_prep_tc(s, (int)p->gate, save ? 1 : 0, p->q, p->k, p->v, p->beta, p->g, t, f, cs); });
         if (e != cudaSuccess) return cuda_fail(e, "prep");
         e = traced("k_prep_wide", cs, [&] { return kda::launch_prep_wide(s, (int)p->gate, p->q, p->k, p->v, p->beta, p->g, t, f, cs); });
         if (e != cudaSuccess) return cuda_fail(e, "prep (wide chunks)");
-        e = traced("k_fwd_scan_tc", cs, [&] { return kda::launch_fwd_scan_tc(s, 1, p->h0, t, f, o, ht, cs); });
+        e = traced("k_fwd_scan_tc", cs, [&] { return kda::launch_fwd_scan_tc(s, save ? 3 : 1, p->h0, t, f, o, ht, cs); });
         if (e != cudaSuccess) return cuda_fail(e, "forward scan");
         return KDA_OK;
     }
@@ -322,6 +359,39 @@ kda_status kda_chunk_bwd(const kda_problem* p, const void* dout, const float* dh
     const kda::Shape s = shape_of(p, d);
     Carver cw{static_cast<char*>(ws)};
     kda::Table t = carve_table(cw, d);
+    if (use_tc(p)) {
+        const bool save = p->save_policy != 0;
+        kda::FwdTC f;
+        if (save) {
+            Carver cs2{static_cast<char*>(const_cast<void*>(saved))};
+            carve_fwd_tc(cs2, d, f, true);
+        } else {
+            carve_fwd_tc(cw, d, f, true);
+        }
+        kda::BwdTC b;
+        kda::Bwd scr;
+        carve_bwd_tc(cw, d, b, scr);
+        const int gate = (int)p->gate;
+        cudaError_t e = traced("k_table", cs, [&] { return kda::launch_table(s, p->B, p->T, p->cu_seqlens, t, cs); });
+        if (e != cudaSuccess) return cuda_fail(e, "chunk table");
+        if (!save) {
+            e = traced("k_prep_tc", cs, [&] { return kda::launch_prep_tc(s, gate, 1, p->q, p->k, p->v, p->beta, p->g, t, f, cs); });
+            if (e != cudaSuccess) return cuda_fail(e, "prep (recompute)");
+            e = traced("k_prep_wide", cs, [&] { return kda::launch_prep_wide(s, gate, p->q, p->k, p->v, p->beta, p->g, t, f, cs); });
+            if (e != cudaSuccess) return cuda_fail(e, "prep (recompute, wide chunks)");
+            e = traced("k_fwd_scan_tc_recompute", cs, [&] { return kda::launch_fwd_scan_tc(s, 2, p->h0, t, f, nullptr, nullptr, cs); });
+            if (e != cudaSuccess) return cuda_fail(e, "forward scan (recompute)");
+        }
+        e = traced("k_bwd_scan_tc", cs, [&] { return kda::launch_bwd_scan_tc(s, dout, dht, t, f, b, dh0, cs); });
+        if (e != cudaSuccess) return cuda_fail(e, "reverse scan");
+        e = traced("k_bwd_consumer_tc", cs, [&] { return kda::launch_bwd_consumer_tc(s, gate, p->q, p->k, p->v, p->beta, p->g, dout, t, f, b, dq, dk, dv, dbeta, dg, cs); });
+        if (e != cudaSuccess) return cuda_fail(e, "consumer");
+        if (gate == KDA_GATE_CHANNEL) {
+            e = traced("k_bwd_wide", cs, [&] { return kda::launch_bwd_wide(s, gate, p->q, p->k, p->v, p->beta, p->g, dout, t, f, b, scr, dq, dk, dv, dbeta, dg, cs); });
+            if (e != cudaSuccess) return cuda_fail(e, "consumer (wide chunks)");
+        }
+        return KDA_OK;
+    }
     kda::Fwd f;
     if (p->save_policy) {
         Carver cs2{static_cast<char*>(const_cast<void*>(saved))};

@@ -28,10 +28,14 @@ namespace {
 
 constexpr int SL = 32;  // value columns of S per slice in k_bwd_dstate
 
-template <typename TI, int D>
+// IT: element type of the P, R, S and S+bar inputs (fp32 here, bf16 when
+// finishing the wide chunks of the tensor-core path, selected by `only`).
+template <typename TI, typename IT, int D>
 __global__ void __launch_bounds__(NTHREADS, 1)
     k_bwd_dstate(Shape s, const TI* __restrict__ dout, const TI* __restrict__ v,
-                 const TI* __restrict__ beta, Table t, Fwd f, Bwd b, TI* __restrict__ dv) {
+                 const TI* __restrict__ beta, Table t, const IT* __restrict__ Pin,
+                 const IT* __restrict__ Rin, const IT* __restrict__ Sin, const IT* __restrict__ SBin,
+                 const int32_t* __restrict__ only, Bwd b, TI* __restrict__ dv) {
     constexpr int LD = D + 1, LS = SL + 1;
     extern __shared__ float smem[];
     float* sO = smem;              // [BT][LD] dO
@@ -46,15 +50,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int tok0 = t.chunk_tok0[c];
     const int H = s.H;
     const size_t ch = (size_t)c * H + h;
+    if (only && !only[ch]) return;
     const int lane = tid & 31, warp = tid >> 5;
 
-    const float* P = b.P + ch * BT * D;
-    const float* R = f.R + ch * BT * D;
+    const IT* P = Pin + ch * BT * D;
+    const IT* R = Rin + ch * BT * D;
     for (int idx = tid; idx < BT * D; idx += NTHREADS) {
         const int r = idx / D, col = idx % D;
         sO[r * LD + col] = (r < len) ? ld(dout + ((size_t)(tok0 + r) * H + h) * D + col) : 0.f;
-        sP[r * LD + col] = P[idx];
-        sR[r * LD + col] = R[idx];
+        sP[r * LD + col] = ld(P + idx);
+        sR[r * LD + col] = ld(R + idx);
     }
     __syncthreads();
     // dv = beta P and <v_i, P_i>, one warp per row
@@ -104,14 +109,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     constexpr int TPR = NTHREADS / D;          // threads per key row for the rowsum
     const int kr = tid / TPR, kpart = tid % TPR;
     float lam = 0.f;
-    const float* SIN = f.SIN + ch * D * D;
-    const float* SBP = b.SBP + ch * D * D;
+    const IT* SIN = Sin + ch * D * D;
+    const IT* SBP = SBin + ch * D * D;
     for (int vs = 0; vs < D; vs += SL) {
         __syncthreads();
         for (int idx = tid; idx < D * SL; idx += NTHREADS) {
             const int r = idx / SL, cc = idx % SL;
-            sS[r * LS + cc] = SIN[(size_t)r * D + vs + cc];
-            sT[r * LS + cc] = SBP[(size_t)r * D + vs + cc];
+            sS[r * LS + cc] = ld(SIN + (size_t)r * D + vs + cc);
+            sT[r * LS + cc] = ld(SBP + (size_t)r * D + vs + cc);
         }
         __syncthreads();
         tile_gemm<BT, D, 8, TN>(aQ, 0, SL, [&](int m, int kk) { return sO[m * LD + vs + kk]; },
@@ -142,9 +147,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 template <typename TI, int D, int GATE>
 __global__ void __launch_bounds__(NTHREADS, 1)
     k_bwd_intra(Shape s, const TI* __restrict__ q, const TI* __restrict__ k,
-                const TI* __restrict__ beta, const float* __restrict__ g, Table t, Fwd f, Bwd b,
-                TI* __restrict__ dq, TI* __restrict__ dk, TI* __restrict__ dbeta,
-                float* __restrict__ dg) {
+                const TI* __restrict__ beta, const float* __restrict__ g, Table t,
+                const int32_t* __restrict__ only, Bwd b, TI* __restrict__ dq, TI* __restrict__ dk,
+                TI* __restrict__ dbeta, float* __restrict__ dg) {
     constexpr int LD = D + 1, LA = BT + 1;
     extern __shared__ float smem[];
     float* sK = smem;               // [BT][LD] keys
@@ -166,6 +171,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const size_t ch = (size_t)c * H + h;
     const float scale = s.scale;
     const int lane = tid & 31, warp = tid >> 5;
+    if (only && !only[ch]) return;
 
     for (int idx = tid; idx < BT * D; idx += NTHREADS) {
         const int r = idx / D, col = idx % D;
@@ -456,22 +462,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
 }
 
-template <typename TI, int D>
+template <typename TI, typename IT, int D>
 cudaError_t run_dstate(const Shape& s, const void* dout, const void* v, const void* beta, Table t,
-                       Fwd f, Bwd b, void* dv, cudaStream_t st) {
+                       const IT* P, const IT* R, const IT* S, const IT* SB, const int32_t* only, Bwd b,
+                       void* dv, cudaStream_t st) {
     constexpr int LD = D + 1, LS = SL + 1;
     constexpr size_t smem = sizeof(float) * (3 * BT * LD + 2 * D * LS);
-    auto kern = k_bwd_dstate<TI, D>;
-    cudaError_t e = set_smem_once<k_bwd_dstate<TI, D>>(smem);
+    auto kern = k_bwd_dstate<TI, IT, D>;
+    cudaError_t e = set_smem_once<k_bwd_dstate<TI, IT, D>>(smem);
     if (e != cudaSuccess) return e;
     dim3 grid(s.NC, s.H);
-    kern<<<grid, NTHREADS, smem, st>>>(s, (const TI*)dout, (const TI*)v, (const TI*)beta, t, f, b, (TI*)dv);
+    kern<<<grid, NTHREADS, smem, st>>>(s, (const TI*)dout, (const TI*)v, (const TI*)beta, t, P, R, S, SB,
+                                       only, b, (TI*)dv);
     return cudaGetLastError();
 }
 
 template <typename TI, int D, int GATE>
 cudaError_t run_intra(const Shape& s, const void* q, const void* k, const void* beta, const float* g,
-                      Table t, Fwd f, Bwd b, void* dq, void* dk, void* dbeta, float* dg,
+                      Table t, const int32_t* only, Bwd b, void* dq, void* dk, void* dbeta, float* dg,
                       cudaStream_t st) {
     constexpr int LD = D + 1, LA = BT + 1;
     constexpr size_t smem = sizeof(float) * (5 * BT * LD + 2 * BT * LA + 2 * BT + D);
@@ -479,19 +487,19 @@ cudaError_t run_intra(const Shape& s, const void* q, const void* k, const void* 
     cudaError_t e = set_smem_once<k_bwd_intra<TI, D, GATE>>(smem);
     if (e != cudaSuccess) return e;
     dim3 grid(s.NC, s.H);
-    kern<<<grid, NTHREADS, smem, st>>>(s, (const TI*)q, (const TI*)k, (const TI*)beta, g, t, f, b,
+    kern<<<grid, NTHREADS, smem, st>>>(s, (const TI*)q, (const TI*)k, (const TI*)beta, g, t, only, b,
                                        (TI*)dq, (TI*)dk, (TI*)dbeta, dg);
     return cudaGetLastError();
 }
 
 template <typename TI, int D>
 cudaError_t run_intra_gate(int gate, const Shape& s, const void* q, const void* k, const void* beta,
-                           const float* g, Table t, Fwd f, Bwd b, void* dq, void* dk, void* dbeta,
-                           float* dg, cudaStream_t st) {
+                           const float* g, Table t, const int32_t* only, Bwd b, void* dq, void* dk,
+                           void* dbeta, float* dg, cudaStream_t st) {
     switch (gate) {
-        case 0: return run_intra<TI, D, 0>(s, q, k, beta, g, t, f, b, dq, dk, dbeta, dg, st);
-        case 1: return run_intra<TI, D, 1>(s, q, k, beta, g, t, f, b, dq, dk, dbeta, dg, st);
-        default: return run_intra<TI, D, 2>(s, q, k, beta, g, t, f, b, dq, dk, dbeta, dg, st);
+        case 0: return run_intra<TI, D, 0>(s, q, k, beta, g, t, only, b, dq, dk, dbeta, dg, st);
+        case 1: return run_intra<TI, D, 1>(s, q, k, beta, g, t, only, b, dq, dk, dbeta, dg, st);
+        default: return run_intra<TI, D, 2>(s, q, k, beta, g, t, only, b, dq, dk, dbeta, dg, st);
     }
 }
 
@@ -500,20 +508,31 @@ cudaError_t run_intra_gate(int gate, const Shape& s, const void* q, const void* 
 cudaError_t launch_bwd_dstate(const Shape& s, int io_bf16, const void* dout, const void* v,
                               const void* beta, Table t, Fwd f, Bwd b, void* dv, cudaStream_t st) {
     if (s.K == 128)
-        return io_bf16 ? run_dstate<__nv_bfloat16, 128>(s, dout, v, beta, t, f, b, dv, st)
-                       : run_dstate<float, 128>(s, dout, v, beta, t, f, b, dv, st);
-    return io_bf16 ? run_dstate<__nv_bfloat16, 64>(s, dout, v, beta, t, f, b, dv, st)
-                   : run_dstate<float, 64>(s, dout, v, beta, t, f, b, dv, st);
+        return io_bf16 ? run_dstate<__nv_bfloat16, float, 128>(s, dout, v, beta, t, b.P, f.R, f.SIN, b.SBP, nullptr, b, dv, st)
+                       : run_dstate<float, float, 128>(s, dout, v, beta, t, b.P, f.R, f.SIN, b.SBP, nullptr, b, dv, st);
+    return io_bf16 ? run_dstate<__nv_bfloat16, float, 64>(s, dout, v, beta, t, b.P, f.R, f.SIN, b.SBP, nullptr, b, dv, st)
+                   : run_dstate<float, float, 64>(s, dout, v, beta, t, b.P, f.R, f.SIN, b.SBP, nullptr, b, dv, st);
 }
 
 cudaError_t launch_bwd_intra(const Shape& s, int io_bf16, int gate, const void* q, const void* k,
                              const void* beta, const float* g, Table t, Fwd f, Bwd b, void* dq,
                              void* dk, void* dbeta, float* dg, cudaStream_t st) {
+    (void)f;
     if (s.K == 128)
-        return io_bf16 ? run_intra_gate<__nv_bfloat16, 128>(gate, s, q, k, beta, g, t, f, b, dq, dk, dbeta, dg, st)
-                       : run_intra_gate<float, 128>(gate, s, q, k, beta, g, t, f, b, dq, dk, dbeta, dg, st);
-    return io_bf16 ? run_intra_gate<__nv_bfloat16, 64>(gate, s, q, k, beta, g, t, f, b, dq, dk, dbeta, dg, st)
-                   : run_intra_gate<float, 64>(gate, s, q, k, beta, g, t, f, b, dq, dk, dbeta, dg, st);
+        return io_bf16 ? run_intra_gate<__nv_bfloat16, 128>(gate, s, q, k, beta, g, t, nullptr, b, dq, dk, dbeta, dg, st)
+                       : run_intra_gate<float, 128>(gate, s, q, k, beta, g, t, nullptr, b, dq, dk, dbeta, dg, st);
+    return io_bf16 ? run_intra_gate<__nv_bfloat16, 64>(gate, s, q, k, beta, g, t, nullptr, b, dq, dk, dbeta, dg, st)
+                   : run_intra_gate<float, 64>(gate, s, q, k, beta, g, t, nullptr, b, dq, dk, dbeta, dg, st);
+}
+
+cudaError_t launch_bwd_wide(const Shape& s, int gate, const void* q, const void* k, const void* v,
+                            const void* beta, const float* g, const void* dout, Table t, FwdTC f,
+                            BwdTC bt, Bwd scratch, void* dq, void* dk, void* dv, void* dbeta, float* dg,
+                            cudaStream_t st) {
+    cudaError_t e = run_dstate<__nv_bfloat16, __nv_bfloat16, 128>(s, dout, v, beta, t, bt.P, f.R, f.HS, bt.SBP,
+                                                                  f.WIDE, scratch, dv, st);
+    if (e != cudaSuccess) return e;
+    return run_intra_gate<__nv_bfloat16, 128>(gate, s, q, k, beta, g, t, f.WIDE, scratch, dq, dk, dbeta, dg, st);
 }
 
 }  // namespace kda

@@ -74,6 +74,12 @@ struct FwdTC {
     __nv_bfloat16* R;     // [NC,H,BT,D]  corrections
 };
 
+// Backward intermediates of the tensor-core path (bf16, [row][col] as named).
+struct BwdTC {
+    __nv_bfloat16* SBP;   // [NC,H,D,D]   adjoint of the state leaving the chunk, [key][value]
+    __nv_bfloat16* P;     // [NC,H,BT,D]  shared sensitivity P = A^T R_bar, [token][value]
+};
+
 // Single-anchor limit of the tensor-core prep (log2 units of the per-feature
 // in-chunk gate range); wider chunks are prepared on CUDA cores.
 constexpr float PREP_RANGE_LOG2 = 80.0f;
@@ -173,6 +179,19 @@ cudaError_t launch_prep_wide(const Shape& s, int gate, const void* q, const void
                              const void* beta, const float* g, Table t, FwdTC ft, cudaStream_t st);
 cudaError_t launch_fwd_scan_tc(const Shape& s, int mode, const float* h0, Table t, FwdTC f, void* o,
                                float* ht, cudaStream_t st);
+
+cudaError_t launch_bwd_scan_tc(const Shape& s, const void* dout, const float* dht, Table t, FwdTC f,
+                               BwdTC b, float* dh0, cudaStream_t st);
+cudaError_t launch_bwd_consumer_tc(const Shape& s, int gate, const void* q, const void* k, const void* v,
+                                   const void* beta, const float* g, const void* dout, Table t, FwdTC f,
+                                   BwdTC b, void* dq, void* dk, void* dv, void* dbeta, float* dg,
+                                   cudaStream_t st);
+// CUDA-core consumers for the WIDE chunks of the tensor-core path (reading its
+// bf16 intermediates, fp32 scratch in `scratch`).
+cudaError_t launch_bwd_wide(const Shape& s, int gate, const void* q, const void* k, const void* v,
+                            const void* beta, const float* g, const void* dout, Table t, FwdTC f,
+                            BwdTC b, Bwd scratch, void* dq, void* dk, void* dv, void* dbeta, float* dg,
+                            cudaStream_t st);
 
 cudaError_t launch_bwd_scan(const Shape& s, int io_bf16, const void* dout, const float* dht,
                             Table t, Fwd f, Bwd b, float* dh0, cudaStream_t st);

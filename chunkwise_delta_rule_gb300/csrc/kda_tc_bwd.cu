@@ -1,0 +1,672 @@
+// Tensor-core backward path (bf16 I/O, K = V = 128) on tcgen05.
+//
+// k_bwd_scan_tc (a8, a9 first product), one CTA per (sequence, head), 128
+// threads, thread v owns value column v. The transposed state adjoint
+// S_bar^T (V x K, fp32) stays in TMEM; chunks are visited last to first:
+//     R_bar^T = S+bar^T F^T + dO^T C_q          ("State and gate composition":
+//                                               both uses of R before the pullback)
+//     P^T     = R_bar^T A                        (Algorithm 1, step 1: P = A^T R_bar)
+//     S_bar^T = S+bar^T diag(lambda) + dO^T Q_g - R_bar^T W
+// where -R_bar^T W is the residual state term -E^T P supplied once
+// ("ReWY: Faster Backpropagation for Delta-Rule Attention", Algorithm 1 step 5
+// and "Complete Reverse Execution and Boundaries"). S+bar and P of every chunk
+// go to HBM (bf16) for the consumer.
+//
+// k_bwd_consumer_tc (a9-a12), one CTA per (chunk slot, head), 256 threads:
+//     [H_q ; -D] = [dO ; P] R^T   (masked: inclusive / strict, sign of D)
+//     [dO S^T ; P S^T] = [dO ; P] S^T        F_bar^T = S+bar R^T
+//     [T_q ; T_e] = [H_q ; D] (K zeta)        (A operand read from TMEM)
+//     T_y^T       = [E_alpha^T | Q_alpha^T] [D ; H_q]
+// with alpha = 2^(G2 - c), zeta = 2^(c - G2) around the per-feature midpoint
+// c ("Matrix intra for vector-gated interactions", centered factors); a scalar
+// gate instead folds 2^(G2_i - G2_j) into H_q and D and uses unit factors, so
+// the key-gradient contractions carry the gate reduction without a key Gram
+// matrix ("Gram elimination for scalar-gate gradients"). Then the chain rule
+// and the reverse in-chunk cumsum of the log-gate gradient ("Complete
+// Reverse Execution and Boundaries", steps 3-4). Per-channel chunks whose
+// gate range needs sub-chunk anchoring are left to the CUDA-core consumers.
+#include "kda_internal.cuh"
+#include "tc.cuh"
+
+namespace kda {
+namespace {
+
+using bf16 = __nv_bfloat16;
+constexpr int D = 128;
+
+__device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, int32_t* err) {
+    bool ok = tc::mbar_wait(bar, parity);
+    ok = __syncthreads_and(ok) != 0;
+    if (!ok && threadIdx.x == 0) atomicOr(err, 2);
+    return ok;
+}
+
+// Copies a row-major bf16 [R][C] global tile (row stride `ld` elements) into a
+// K-major SW128 smem tile; rows >= valid are zero-filled.
+template <int R, int C, int NT>
+__device__ __forceinline__ void load_tile(uint32_t sbase, const bf16* src, size_t ld, int valid, int tid) {
+    constexpr int CPR = C * 2 / 16;
+    for (int idx = tid; idx < R * CPR; idx += NT) {
+        const int r = idx / CPR, cc = idx % CPR;
+        const bool in = r < valid;
+        tc::cp_async16(sbase + tc::sw128_off(R, r, cc * 16), src + (in ? (size_t)r * ld + cc * 8 : 0), in ? 16u : 0u);
+    }
+}
+
+// ====================================================== k_bwd_scan_tc
+constexpr int ST = 128;
+constexpr int B_ASB = 0;        // S+bar^T bf16 [128][128] 32 KB
+constexpr int B_ADO = 32768;    // dO^T    bf16 [128][64]  16 KB
+constexpr int B_ARB = 49152;    // R_bar^T bf16 [128][64]  16 KB
+constexpr int B_ANR = 65536;    // -R_bar^T                16 KB
+constexpr int B_STAGE = 81920;  // two stages of B operands
+constexpr int S_KG = 0;         // F    [64][128] 16 KB
+constexpr int S_AQT = 16384;    // C_q^T [64][64]  8 KB
+constexpr int S_AIT = 24576;    // A^T  [64][64]   8 KB
+constexpr int S_QGT = 32768;    // Q_g^T [128][64] 16 KB
+constexpr int S_WT = 49152;     // W^T  [128][64] 16 KB
+constexpr int B_STG = 65536;
+constexpr int B_LAM = B_STAGE + 2 * B_STG;     // lambda [128] fp32
+constexpr int B_BAR = B_LAM + 512;
+constexpr int BSCAN_SMEM = B_BAR + 64 + 1024;
+
+__device__ __forceinline__ void bscan_prefetch(uint32_t stg, const FwdTC& f, size_t ch, int tid) {
+    load_tile<BT, D, ST>(stg + S_KG, f.KG + ch * BT * D, D, BT, tid);
+    load_tile<BT, BT, ST>(stg + S_AQT, f.AQKT + ch * BT * BT, BT, BT, tid);
+    load_tile<BT, BT, ST>(stg + S_AIT, f.AIT + ch * BT * BT, BT, BT, tid);
+    load_tile<D, BT, ST>(stg + S_QGT, f.QGT + ch * D * BT, BT, D, tid);
+    load_tile<D, BT, ST>(stg + S_WT, f.WT + ch * D * BT, BT, D, tid);
+    tc::cp_async_commit();
+}
+
+__global__ void __launch_bounds__(ST, 1)
+    k_bwd_scan_tc(Shape s, const bf16* __restrict__ dout, const float* __restrict__ dht, Table t, FwdTC f,
+                  BwdTC b, float* __restrict__ dh0) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                           ~static_cast<uintptr_t>(1023));
+    float* sLam = reinterpret_cast<float*>(base + B_LAM);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(base + B_BAR);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 2);
+    const uint32_t sb = tc::smem_u32(base);
+    const int nseq = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5;
+    const int H = s.H;
+    const int vcol = tid;
+    const int c0 = t.seq_chunk0[nseq], c1 = t.seq_chunk0[nseq + 1];
+
+    if (tid == 0) {
+        tc::mbar_init(&bar[0], 1);
+        tc::mbar_init(&bar[1], 1);
+        tc::fence_mbar_init();
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(tslot, 256);
+        tc::tmem_relinquish();
+    }
+    if (c0 < c1) bscan_prefetch(sb + B_STAGE, f, (size_t)(c1 - 1) * H + h, tid);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tb = *tslot;
+    const uint32_t tl = tc::taddr(tb, 32 * warp, 0);
+    const size_t st_off = ((size_t)nseq * H + h) * D * D;
+
+#pragma unroll 1
+    for (int cb = 0; cb < D; cb += 16) {
+        float a[16];
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) a[jj] = dht ? dht[st_off + (size_t)(cb + jj) * D + vcol] : 0.f;
+        tc::tmem_st16(tl + cb, a);
+    }
+    tc::tmem_wait_st();
+
+    uint32_t ph0 = 0, ph1 = 0;
+    bool ok = true;
+    for (int c = c1 - 1; c >= c0 && ok; --c) {
+        const int it = c1 - 1 - c, stage = it & 1;
+        const size_t ch = (size_t)c * H + h;
+        const int len = t.chunk_len[c], tok0 = t.chunk_tok0[c];
+        const uint32_t stg = sb + B_STAGE + stage * B_STG;
+        sLam[tid] = exp2f(f.GL[ch * D + tid]);
+        // dO^T row of this value column
+        {
+            uint4 pk[8];
+            uint32_t* pw = reinterpret_cast<uint32_t*>(pk);
+#pragma unroll
+            for (int i = 0; i < BT; i += 2) {
+                const float x0 = (i < len) ? __bfloat162float(dout[((size_t)(tok0 + i) * H + h) * D + vcol]) : 0.f;
+                const float x1 = (i + 1 < len) ? __bfloat162float(dout[((size_t)(tok0 + i + 1) * H + h) * D + vcol]) : 0.f;
+                pw[i / 2] = tc::pack_bf16(x0, x1);
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q) *reinterpret_cast<uint4*>(base + B_ADO + tc::sw128_off(D, vcol, q * 16)) = pk[q];
+        }
+        __syncthreads();
+        // S+bar^T -> bf16 operand and HBM; then S_bar^T <- S+bar^T diag(lambda)
+        bf16* SBP = b.SBP + ch * D * D;
+#pragma unroll 1
+        for (int cb = 0; cb < D; cb += 16) {
+            float a[16];
+            tc::tmem_ld16(tl + cb, a);
+            tc::tmem_wait_ld();
+            uint4 pk[2];
+            uint32_t* pw = reinterpret_cast<uint32_t*>(pk);
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) pw[jj] = tc::pack_bf16(a[2 * jj], a[2 * jj + 1]);
+            *reinterpret_cast<uint4*>(base + B_ASB + tc::sw128_off(D, vcol, cb * 2)) = pk[0];
+            *reinterpret_cast<uint4*>(base + B_ASB + tc::sw128_off(D, vcol, cb * 2 + 16)) = pk[1];
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) SBP[(size_t)(cb + jj) * D + vcol] = __float2bfloat16_rn(a[jj]);
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) a[jj] *= sLam[cb + jj];
+            tc::tmem_st16(tl + cb, a);
+        }
+        tc::tmem_wait_st();
+        tc::cp_async_wait_all();
+        tc::fence_async_smem();
+        tc::fence_before_sync();
+        __syncthreads();
+        if (tid == 0) {
+            tc::fence_after_sync();
+            const uint32_t i64 = tc::idesc_bf16(128, 64), i128 = tc::idesc_bf16(128, 128);
+#pragma unroll 1
+            for (int ks = 0; ks < 8; ++ks)
+                tc::mma_bf16(tb + 128, tc::sdesc_k(sb + B_ASB, D, ks), tc::sdesc_k(stg + S_KG, BT, ks), i64, ks > 0);
+#pragma unroll 1
+            for (int ks = 0; ks < 4; ++ks)
+                tc::mma_bf16(tb + 128, tc::sdesc_k(sb + B_ADO, D, ks), tc::sdesc_k(stg + S_AQT, BT, ks), i64, 1);
+#pragma unroll 1
+            for (int ks = 0; ks < 4; ++ks)
+                tc::mma_bf16(tb, tc::sdesc_k(sb + B_ADO, D, ks), tc::sdesc_k(stg + S_QGT, D, ks), i128, 1);
+            tc::mma_commit(&bar[0]);
+        }
+        if (c - 1 >= c0) bscan_prefetch(sb + B_STAGE + (stage ^ 1) * B_STG, f, (size_t)(c - 1) * H + h, tid);
+        ok = wait_all(&bar[0], ph0, t.err);
+        ph0 ^= 1;
+        if (!ok) break;
+        tc::fence_after_sync();
+        // R_bar^T -> bf16 operands (and its negation)
+#pragma unroll
+        for (int cb = 0; cb < BT; cb += 16) {
+            float a[16];
+            tc::tmem_ld16(tl + 128 + cb, a);
+            tc::tmem_wait_ld();
+            uint4 pk[2], nk[2];
+            uint32_t* pw = reinterpret_cast<uint32_t*>(pk);
+            uint32_t* nw = reinterpret_cast<uint32_t*>(nk);
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+                pw[jj] = tc::pack_bf16(a[2 * jj], a[2 * jj + 1]);
+                nw[jj] = tc::pack_bf16(-a[2 * jj], -a[2 * jj + 1]);
+            }
+            *reinterpret_cast<uint4*>(base + B_ARB + tc::sw128_off(D, vcol, cb * 2)) = pk[0];
+            *reinterpret_cast<uint4*>(base + B_ARB + tc::sw128_off(D, vcol, cb * 2 + 16)) = pk[1];
+            *reinterpret_cast<uint4*>(base + B_ANR + tc::sw128_off(D, vcol, cb * 2)) = nk[0];
+            *reinterpret_cast<uint4*>(base + B_ANR + tc::sw128_off(D, vcol, cb * 2 + 16)) = nk[1];
+        }
+        tc::fence_async_smem();
+        tc::fence_before_sync();
+        __syncthreads();
+        if (tid == 0) {
+            tc::fence_after_sync();
+            const uint32_t i64 = tc::idesc_bf16(128, 64), i128 = tc::idesc_bf16(128, 128);
+#pragma unroll 1
+            for (int ks = 0; ks < 4; ++ks)
+                tc::mma_bf16(tb + 192, tc::sdesc_k(sb + B_ARB, D, ks), tc::sdesc_k(stg + S_AIT, BT, ks), i64, ks > 0);
+#pragma unroll 1
+            for (int ks = 0; ks < 4; ++ks)
+                tc::mma_bf16(tb, tc::sdesc_k(sb + B_ANR, D, ks), tc::sdesc_k(stg + S_WT, D, ks), i128, 1);
+            tc::mma_commit(&bar[1]);
+        }
+        ok = wait_all(&bar[1], ph1, t.err);
+        ph1 ^= 1;
+        if (!ok) break;
+        tc::fence_after_sync();
+        bf16* P = b.P + ch * BT * D;
+#pragma unroll 1
+        for (int cb = 0; cb < BT; cb += 16) {
+            float a[16];
+            tc::tmem_ld16(tl + 192 + cb, a);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) P[(size_t)(cb + jj) * D + vcol] = __float2bfloat16_rn(a[jj]);
+        }
+        tc::fence_before_sync();
+        __syncthreads();
+    }
+    if (ok && dh0) {
+        tc::fence_after_sync();
+#pragma unroll 1
+        for (int cb = 0; cb < D; cb += 16) {
+            float a[16];
+            tc::tmem_ld16(tl + cb, a);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) dh0[st_off + (size_t)(cb + jj) * D + vcol] = a[jj];
+        }
+    }
+    tc::cp_async_wait_all();
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tb, 256);
+}
+
+// ================================================== k_bwd_consumer_tc
+constexpr int CT = 256;
+constexpr int LG = D + 1;
+// region X (128 KB): phase A operands, then phase B operands, then final tiles
+constexpr int X_OP = 0;          // [dO ; P]   bf16 [128][128]   32 KB
+constexpr int X_R = 32768;       // R          bf16 [64][128]    16 KB
+constexpr int X_S = 49152;       // S          bf16 [128][128]   32 KB
+constexpr int X_SB = 81920;      // S+bar      bf16 [128][128]   32 KB
+constexpr int X_EQ = 0;          // [E_a^T | Q_a^T] tf32 [128][128] 64 KB
+constexpr int X_KZ = 65536;      // (K zeta)^T tf32 [128][64]    32 KB
+constexpr int X_DH = 98304;      // [D ; H_q]^T tf32 [64][128]   32 KB
+constexpr int X_BYTES = 131072;
+constexpr int C_G = X_BYTES;                      // G2 fp32 [64][129]
+constexpr int C_K = C_G + 4 * BT * LG;            // k bf16 [64][128]
+constexpr int C_Q = C_K + 2 * BT * D;             // q bf16 [64][128]
+constexpr int C_MISC = C_Q + 2 * BT * D;          // small arrays
+constexpr int M_BETA = 0, M_C = 64, M_LAMB = 192, M_DBW = 320, M_ROWA = 384, M_ROWB = 448,
+              M_ENDA = 512, M_ENDB = 640, M_ROW = 768;   // float offsets
+constexpr int C_BAR = C_MISC + 4 * 832;
+constexpr int CONS_SMEM = C_BAR + 64 + 1024;
+
+__device__ __forceinline__ float bfx(const bf16* p) { return __bfloat162float(*p); }
+
+template <int GATE>
+__global__ void __launch_bounds__(CT, 1)
+    k_bwd_consumer_tc(Shape s, const bf16* __restrict__ q, const bf16* __restrict__ k,
+                      const bf16* __restrict__ v, const bf16* __restrict__ beta, const float* __restrict__ g,
+                      const bf16* __restrict__ dout, Table t, FwdTC f, BwdTC b, bf16* __restrict__ dq,
+                      bf16* __restrict__ dk, bf16* __restrict__ dv, bf16* __restrict__ dbeta,
+                      float* __restrict__ dg) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                           ~static_cast<uintptr_t>(1023));
+    float* sG = reinterpret_cast<float*>(base + C_G);
+    bf16* sK = reinterpret_cast<bf16*>(base + C_K);
+    bf16* sQ = reinterpret_cast<bf16*>(base + C_Q);
+    float* sm = reinterpret_cast<float*>(base + C_MISC);
+    float* sBeta = sm + M_BETA;
+    float* sC = sm + M_C;
+    float* sLamb = sm + M_LAMB;
+    float* sDbw = sm + M_DBW;
+    float* sRowA = sm + M_ROWA;
+    float* sRowB = sm + M_ROWB;
+    float* sEndA = sm + M_ENDA;
+    float* sEndB = sm + M_ENDB;
+    float* sRow = sm + M_ROW;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(base + C_BAR);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 1);
+    const uint32_t sb = tc::smem_u32(base);
+
+    const int c = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int n = t.chunk_len[c];
+    if (n <= 0) return;
+    const int H = s.H;
+    const size_t ch = (size_t)c * H + h;
+    if (GATE == 2 && f.WIDE[ch]) return;  // sub-chunk anchoring: CUDA-core consumers
+    const int tok0 = t.chunk_tok0[c];
+    const float scale = s.scale;
+    const size_t rowstride = (size_t)H * D;
+
+    if (tid == 0) {
+        tc::mbar_init(bar, 1);
+        tc::fence_mbar_init();
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(tslot, 512);
+        tc::tmem_relinquish();
+    }
+    // phase A operands by cp.async: [dO ; P], R, S, S+bar
+    {
+        // one 128-row tile: rows 0..63 = dO (token rows, zero past the chunk), rows 64..127 = P
+        const bf16* dO0 = dout + ((size_t)tok0 * H + h) * D;
+        const bf16* P0 = b.P + ch * BT * D;
+        for (int idx = tid; idx < 2 * BT * 16; idx += CT) {
+            const int r = idx >> 4, cc = idx & 15;
+            const bool isO = r < BT;
+            const bool in = !isO || r < n;
+            const bf16* src = isO ? dO0 + (in ? (size_t)r * rowstride + cc * 8 : 0) : P0 + (size_t)(r - BT) * D + cc * 8;
+            tc::cp_async16(sb + X_OP + tc::sw128_off(2 * BT, r, cc * 16), src, in ? 16u : 0u);
+        }
+        load_tile<BT, D, CT>(sb + X_R, f.R + ch * BT * D, D, BT, tid);
+        load_tile<D, D, CT>(sb + X_S, f.HS + ch * D * D, D, D, tid);
+        load_tile<D, D, CT>(sb + X_SB, b.SBP + ch * D * D, D, D, tid);
+        tc::cp_async_commit();
+    }
+    // raw inputs: k, q (bf16 rows), g (log2 units), beta
+    for (int idx = tid; idx < BT * 16; idx += CT) {
+        const int r = idx >> 4, cc = idx & 15;
+        uint4 kv = make_uint4(0, 0, 0, 0), qv = make_uint4(0, 0, 0, 0);
+        if (r < n) {
+            const size_t off = ((size_t)(tok0 + r) * H + h) * D + cc * 8;
+            kv = *reinterpret_cast<const uint4*>(k + off);
+            qv = *reinterpret_cast<const uint4*>(q + off);
+        }
+        *reinterpret_cast<uint4*>(sK + r * D + cc * 8) = kv;
+        *reinterpret_cast<uint4*>(sQ + r * D + cc * 8) = qv;
+    }
+    for (int idx = tid; idx < BT * D; idx += CT) {
+        const int r = idx >> 7, col = idx & (D - 1);
+        float gv = 0.f;
+        if (r < n) {
+            if (GATE == 2) gv = g[((size_t)(tok0 + r) * H + h) * D + col] * LOG2E;
+            if (GATE == 1) gv = g[(size_t)(tok0 + r) * H + h] * LOG2E;
+        }
+        sG[r * LG + col] = gv;
+    }
+    if (tid < BT) sBeta[tid] = (tid < n) ? bfx(beta + (size_t)(tok0 + tid) * H + h) : 0.f;
+    // dv = beta P and <v_i, P_i>: warp w handles rows w, w+8, ..
+    for (int r = warp; r < BT; r += CT / 32) {
+        float acc = 0.f;
+        if (r < n) {
+            const size_t tok = (size_t)(tok0 + r) * H + h;
+            const float bt = bfx(beta + tok);
+            const bf16* Pr = b.P + ch * BT * D + (size_t)r * D + lane * 4;
+            const bf16* vr = v + tok * D + lane * 4;
+            uint32_t out[2];
+#pragma unroll
+            for (int e = 0; e < 4; e += 2) {
+                const float p0 = bfx(Pr + e), p1 = bfx(Pr + e + 1);
+                acc = fmaf(bfx(vr + e), p0, acc);
+                acc = fmaf(bfx(vr + e + 1), p1, acc);
+                out[e / 2] = tc::pack_bf16(bt * p0, bt * p1);
+            }
+            *reinterpret_cast<uint2*>(dv + tok * D + lane * 4) = make_uint2(out[0], out[1]);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0) sDbw[r] = acc;
+    }
+    tc::cp_async_wait_all();
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tb = *tslot;
+    // TMEM columns: [0,64) [H_q ; -D] -> [H_q ; D] ; [64,192) [dO S^T ; P S^T] ;
+    // [192,256) F_bar^T ; [256,384) [T_q ; T_e] ; [384,448) T_y^T
+    if (tid == 0) {
+        const uint32_t i64 = tc::idesc_bf16(128, 64), i128 = tc::idesc_bf16(128, 128);
+#pragma unroll 1
+        for (int ks = 0; ks < 8; ++ks)
+            tc::mma_bf16(tb, tc::sdesc_k(sb + X_OP, D, ks), tc::sdesc_k(sb + X_R, BT, ks), i64, ks > 0);
+#pragma unroll 1
+        for (int ks = 0; ks < 8; ++ks)
+            tc::mma_bf16(tb + 64, tc::sdesc_k(sb + X_OP, D, ks), tc::sdesc_k(sb + X_S, D, ks), i128, ks > 0);
+#pragma unroll 1
+        for (int ks = 0; ks < 8; ++ks)
+            tc::mma_bf16(tb + 192, tc::sdesc_k(sb + X_SB, D, ks), tc::sdesc_k(sb + X_R, BT, ks), i64, ks > 0);
+        tc::mma_commit(bar);
+    }
+    // while the MMAs run: cumsum, centers, rowsum(S .* S+bar) from HBM
+    if (tid < D) {
+        float acc = 0.f;
+        for (int r = 0; r < BT; ++r) {
+            acc += sG[r * LG + tid];
+            sG[r * LG + tid] = acc;
+        }
+        float hi = sG[tid], lo = sG[tid];
+        for (int r = 1; r < n; ++r) {
+            hi = fmaxf(hi, sG[r * LG + tid]);
+            lo = fminf(lo, sG[r * LG + tid]);
+        }
+        sC[tid] = (GATE == 2) ? 0.5f * (hi + lo) : 0.f;
+    } else {
+        const int kr = tid - D;
+        const uint4* hs = reinterpret_cast<const uint4*>(f.HS + ch * D * D + (size_t)kr * D);
+        const uint4* sbp = reinterpret_cast<const uint4*>(b.SBP + ch * D * D + (size_t)kr * D);
+        float acc = 0.f;
+#pragma unroll 4
+        for (int cc = 0; cc < 16; ++cc) {
+            const uint4 a = hs[cc], bb = sbp[cc];
+            const bf16* pa = reinterpret_cast<const bf16*>(&a);
+            const bf16* pb = reinterpret_cast<const bf16*>(&bb);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc = fmaf(__bfloat162float(pa[e]), __bfloat162float(pb[e]), acc);
+        }
+        sLamb[kr] = acc;
+    }
+    bool ok = wait_all(bar, 0, t.err);
+    if (ok) {
+        tc::fence_after_sync();
+        // ---- epilogue A: mask [H_q ; -D] into [H_q ; D] (scalar gate: fold the pairwise decay),
+        // keep it in TMEM as the A operand of [T_q ; T_e], and write its transpose as B of T_y^T
+        {
+            const int row = 32 * (warp & 3) + lane, cb0 = (warp >> 2) * 32;
+            const uint32_t ta = tc::taddr(tb, 32 * (warp & 3), cb0);
+            float a[32];
+            tc::tmem_ld16(ta, *reinterpret_cast<float(*)[16]>(a));
+            tc::tmem_ld16(ta + 16, *reinterpret_cast<float(*)[16]>(a + 16));
+            tc::tmem_wait_ld();
+            const bool isH = row < BT;
+            const int i = isH ? row : row - BT;
+            const float gi = sG[i * LG];
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) {
+                const int j = cb0 + jj;
+                float x = (i < n && (isH ? j <= i : j < i)) ? (isH ? a[jj] : -a[jj]) : 0.f;
+                if (GATE == 1) x *= exp2f(fminf(gi - sG[j * LG], 0.f));
+                a[jj] = x;
+                const int kidx = isH ? BT + i : i;   // K order of T_y^T: D rows first, then H_q rows
+                *reinterpret_cast<float*>(base + X_DH + tc::sw128_off(BT, j, kidx * 4)) = x;
+            }
+            tc::tmem_st16(ta, *reinterpret_cast<float(*)[16]>(a));
+            tc::tmem_st16(ta + 16, *reinterpret_cast<float(*)[16]>(a + 16));
+            tc::tmem_wait_st();
+        }
+        // (K zeta)^T: rows = key k, K = token j
+        for (int idx = tid; idx < D * 16; idx += CT) {
+            const int kr = idx & (D - 1), cc = idx >> 7;
+            float4 val;
+            float* pv = reinterpret_cast<float*>(&val);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int j = 4 * cc + e;
+                const float kv = __bfloat162float(sK[j * D + kr]);
+                pv[e] = (GATE == 2) ? kv * exp2f(sC[kr] - sG[j * LG + kr]) : kv;
+            }
+            *reinterpret_cast<float4*>(base + X_KZ + tc::sw128_off(D, kr, cc * 16)) = val;
+        }
+        // [E_alpha^T | Q_alpha^T]: rows = key k, K = token (E part, then Q part)
+        for (int idx = tid; idx < D * 32; idx += CT) {
+            const int kr = idx & (D - 1), cc = idx >> 7;
+            float4 val;
+            float* pv = reinterpret_cast<float*>(&val);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int kk = 4 * cc + e;
+                const int j = kk & (BT - 1);
+                const float al = (GATE == 2) ? exp2f(sG[j * LG + kr] - sC[kr]) : 1.f;
+                pv[e] = (kk < BT) ? sBeta[j] * __bfloat162float(sK[j * D + kr]) * al
+                                  : scale * __bfloat162float(sQ[j * D + kr]) * al;
+            }
+            *reinterpret_cast<float4*>(base + X_EQ + tc::sw128_off(D, kr, cc * 16)) = val;
+        }
+        tc::fence_async_smem();
+        tc::fence_before_sync();
+        __syncthreads();
+        if (tid == 0) {
+            tc::fence_after_sync();
+            const uint32_t i128 = tc::idesc_tf32(128, 128), i64 = tc::idesc_tf32(128, 64);
+#pragma unroll 1
+            for (int ks = 0; ks < 8; ++ks)
+                tc::mma_tf32_ts(tb + 256, tb + 8 * ks, tc::sdesc_k(sb + X_KZ, D, ks), i128, ks > 0);
+#pragma unroll 1
+            for (int ks = 0; ks < 16; ++ks)
+                tc::mma_tf32(tb + 384, tc::sdesc_k(sb + X_EQ, D, ks), tc::sdesc_k(sb + X_DH, BT, ks), i64, ks > 0);
+            tc::mma_commit(bar);
+        }
+        ok = wait_all(bar, 1, t.err);
+    }
+    if (ok) {
+        tc::fence_after_sync();
+        float* sDK = reinterpret_cast<float*>(base);              // [64][129] beta*gamma*E_bar + Y_bar/gamma
+        float* sGQ = sDK + BT * LG;                               // [64][129] G_bar (query and key-side parts)
+        float* sGE = sGQ + BT * LG;                               // [64][129] G_bar (erase part)
+        // ---- F1: rows of [T_q ; T_e] and [dO S^T ; P S^T]
+        {
+            const int row = 32 * (warp & 3) + lane, cb0 = (warp >> 2) * 64;
+            const bool isQ = row < BT;
+            const int i = isQ ? row : row - BT;
+            const float bt = sBeta[i];
+            float part = 0.f;
+            uint32_t packed[32];
+#pragma unroll
+            for (int cb = 0; cb < 64; cb += 16) {
+                float tq[16], tp[16];
+                tc::tmem_ld16(tc::taddr(tb + 256, 32 * (warp & 3), cb0 + cb), tq);
+                tc::tmem_ld16(tc::taddr(tb + 64, 32 * (warp & 3), cb0 + cb), tp);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) {
+                    const int kr = cb0 + cb + jj;
+                    const float gk = sG[i * LG + kr];
+                    const float al = (GATE == 2) ? exp2f(gk - sC[kr]) : 1.f;
+                    const float gam = exp2f(gk);
+                    if (isQ) {
+                        const float Qt = al * tq[jj] + gam * tp[jj];               // gamma * Q_g_bar
+                        sGQ[i * LG + kr] = scale * __bfloat162float(sQ[i * D + kr]) * Qt;
+                        if (jj & 1) packed[(cb + jj) / 2] = tc::pack_bf16(tq[jj - 1], scale * Qt);
+                        else tq[jj] = scale * Qt;  // stash for the pair
+                    } else {
+                        const float Et = al * tq[jj] - gam * tp[jj];               // gamma * E_bar
+                        const float kv = __bfloat162float(sK[i * D + kr]);
+                        sDK[i * LG + kr] = bt * Et;
+                        sGE[i * LG + kr] = bt * kv * Et;
+                        part = fmaf(kv, Et, part);
+                    }
+                }
+            }
+            if (isQ) {
+                if (i < n) {
+                    uint4* dst = reinterpret_cast<uint4*>(dq + ((size_t)(tok0 + i) * H + h) * D + cb0);
+#pragma unroll
+                    for (int qq = 0; qq < 8; ++qq)
+                        dst[qq] = make_uint4(packed[4 * qq], packed[4 * qq + 1], packed[4 * qq + 2], packed[4 * qq + 3]);
+                }
+            } else {
+                if (warp < 4) sRowA[i] = part;
+                else sRowB[i] = part;
+            }
+        }
+        __syncthreads();
+        // ---- F2: T_y^T and F_bar^T rows = key k, columns = token j
+        {
+            const int kr = 32 * (warp & 3) + lane, cb0 = (warp >> 2) * 32;
+            const float glk = sG[(n - 1) * LG + kr];
+            float endp = 0.f;
+#pragma unroll 1
+            for (int cb = 0; cb < 32; cb += 16) {
+                float ty[16], fb[16];
+                tc::tmem_ld16(tc::taddr(tb + 384, 32 * (warp & 3), cb0 + cb), ty);
+                tc::tmem_ld16(tc::taddr(tb + 192, 32 * (warp & 3), cb0 + cb), fb);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) {
+                    const int j = cb0 + cb + jj;
+                    const float gj = sG[j * LG + kr];
+                    const float ze = (GATE == 2) ? exp2f(sC[kr] - gj) : 1.f;
+                    const float dec = exp2f(glk - gj);                  // lambda / gamma_j
+                    const float Yt = ze * ty[jj] + fb[jj] * dec;        // Y_bar / gamma
+                    const float kv = __bfloat162float(sK[j * D + kr]);
+                    sDK[j * LG + kr] += Yt;
+                    sGQ[j * LG + kr] -= kv * Yt;
+                    if (j < n) endp = fmaf(kv * dec, fb[jj], endp);      // F_j . F_bar_j
+                }
+            }
+            if (warp < 4) sEndA[kr] = endp;
+            else sEndB[kr] = endp;
+        }
+        __syncthreads();
+        // ---- F3: dk, dbeta, dg
+        for (int idx = tid; idx < BT * D / 8; idx += CT) {
+            const int r = idx >> 4, cc = idx & 15;
+            if (r < n) {
+                uint4 pk;
+                uint32_t* pw = reinterpret_cast<uint32_t*>(&pk);
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    pw[e] = tc::pack_bf16(sDK[r * LG + cc * 8 + 2 * e], sDK[r * LG + cc * 8 + 2 * e + 1]);
+                *reinterpret_cast<uint4*>(dk + ((size_t)(tok0 + r) * H + h) * D + cc * 8) = pk;
+            }
+        }
+        if (tid < BT && tid < n)
+            dbeta[(size_t)(tok0 + tid) * H + h] = __float2bfloat16_rn(sRowA[tid] + sRowB[tid] + sDbw[tid]);
+        if (GATE != 0) {
+            if (tid < D) {
+                const float glk = sG[(n - 1) * LG + tid];
+                const float endp = exp2f(glk) * sLamb[tid] + sEndA[tid] + sEndB[tid];
+                sGQ[(n - 1) * LG + tid] += endp;
+            }
+            __syncthreads();
+            if (GATE == 2) {
+                if (tid < D) {
+                    float acc = 0.f;
+                    for (int r = n - 1; r >= 0; --r) {
+                        acc += sGQ[r * LG + tid] + sGE[r * LG + tid];
+                        dg[((size_t)(tok0 + r) * H + h) * D + tid] = acc;
+                    }
+                }
+            } else {
+                for (int r = warp; r < BT; r += CT / 32) {
+                    float x = 0.f;
+                    for (int col = lane; col < D; col += 32) x += sGQ[r * LG + col] + sGE[r * LG + col];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+                    if (lane == 0) sRow[r] = x;
+                }
+                __syncthreads();
+                if (tid == 0) {
+                    float acc = 0.f;
+                    for (int r = n - 1; r >= 0; --r) {
+                        acc += sRow[r];
+                        dg[(size_t)(tok0 + r) * H + h] = acc;
+                    }
+                }
+            }
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tb, 512);
+}
+
+template <int GATE>
+cudaError_t run_consumer(const Shape& s, const void* q, const void* k, const void* v, const void* beta,
+                         const float* g, const void* dout, Table t, FwdTC f, BwdTC b, void* dq, void* dk,
+                         void* dv, void* dbeta, float* dg, cudaStream_t st) {
+    cudaError_t e = set_smem_once<k_bwd_consumer_tc<GATE>>(CONS_SMEM);
+    if (e != cudaSuccess) return e;
+    dim3 grid(s.NC, s.H);
+    k_bwd_consumer_tc<GATE><<<grid, CT, CONS_SMEM, st>>>(
+        s, (const bf16*)q, (const bf16*)k, (const bf16*)v, (const bf16*)beta, g, (const bf16*)dout, t, f, b,
+        (bf16*)dq, (bf16*)dk, (bf16*)dv, (bf16*)dbeta, dg);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_scan_tc(const Shape& s, const void* dout, const float* dht, Table t, FwdTC f, BwdTC b,
+                               float* dh0, cudaStream_t st) {
+    cudaError_t e = set_smem_once<k_bwd_scan_tc>(BSCAN_SMEM);
+    if (e != cudaSuccess) return e;
+    dim3 grid(s.N, s.H);
+    k_bwd_scan_tc<<<grid, ST, BSCAN_SMEM, st>>>(s, (const bf16*)dout, dht, t, f, b, dh0);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_consumer_tc(const Shape& s, int gate, const void* q, const void* k, const void* v,
+                                   const void* beta, const float* g, const void* dout, Table t, FwdTC f,
+                                   BwdTC b, void* dq, void* dk, void* dv, void* dbeta, float* dg,
+                                   cudaStream_t st) {
+    switch (gate) {
+        case 0: return run_consumer<0>(s, q, k, v, beta, g, dout, t, f, b, dq, dk, dv, dbeta, dg, st);
+        case 1: return run_consumer<1>(s, q, k, v, beta, g, dout, t, f, b, dq, dk, dv, dbeta, dg, st);
+        default: return run_consumer<2>(s, q, k, v, beta, g, dout, t, f, b, dq, dk, dv, dbeta, dg, st);
+    }
+}
+
+}  // namespace kda

@@ -344,11 +344,9 @@ constexpr int STG_BYTES = 57344;
 constexpr int OFF_BAR = OFF_STAGE + 2 * STG_BYTES;
 constexpr int SCAN_SMEM = OFF_BAR + 64 + 1024;
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+using tc::cp_async16;
+using tc::cp_async_commit;
+using tc::cp_async_wait_all;
 
 // Copies a row-major bf16 [R][C] global tile into a K-major SW128 smem tile.
 template <int R, int C>

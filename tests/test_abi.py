@@ -67,7 +67,15 @@ def test_workspace_size_arithmetic():
     ptc = _prob(io=0)
     ftc = up(2 * chd * BT * D) * 3 + up(2 * chd * BT * BT) + up(4 * chd * BT * D) + up(4 * chd * D) + up(4 * chd)
     assert _ws(ptc, 0) == table + ftc
-    pa = _prob(save=1)
+    ftc_b = up(2 * chd * BT * D) * 3 + up(2 * chd * BT * BT) * 2 + up(2 * chd * D * D) + up(2 * chd * BT * D)
+    btc = up(2 * chd * D * D) + up(2 * chd * BT * D)
+    wscr = up(4 * chd * BT * D) * 3 + up(4 * chd * BT * BT) * 2 + up(4 * chd * D) + up(4 * chd * BT)
+    assert _ws(ptc, 1) == table + ftc + ftc_b + btc + wscr
+    ptca = _prob(io=0, save=1)
+    assert _ws(ptca, 0) == table
+    assert _ws(ptca, 1) == table + btc + wscr
+    assert _lib.load().kda_saved_size(ctypes.byref(ptca)) == ftc + ftc_b
+    pa = _prob(save=1, io=1)
     assert _ws(pa, 0) == table
     assert _ws(pa, 1) == table + bwd
     assert _lib.load().kda_saved_size(ctypes.byref(pa)) == fcore + fextra
