@@ -386,7 +386,7 @@ kda_status kda_chunk_bwd(const kda_problem* p, const void* dout, const float* dh
         if (e != cudaSuccess) return cuda_fail(e, "reverse scan");
         e = traced("k_bwd_consumer_tc", cs, [&] { return kda::launch_bwd_consumer_tc(s, gate, p->q, p->k, p->v, p->beta, p->g, dout, t, f, b, dq, dk, dv, dbeta, dg, cs); });
         if (e != cudaSuccess) return cuda_fail(e, "consumer");
-        if (gate == KDA_GATE_CHANNEL) {
+        if (gate != KDA_GATE_NONE) {
             e = traced("k_bwd_wide", cs, [&] { return kda::launch_bwd_wide(s, gate, p->q, p->k, p->v, p->beta, p->g, dout, t, f, b, scr, dq, dk, dv, dbeta, dg, cs); });
             if (e != cudaSuccess) return cuda_fail(e, "consumer (wide chunks)");
         }

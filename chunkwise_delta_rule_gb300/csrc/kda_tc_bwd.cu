@@ -23,8 +23,10 @@
 // the key-gradient contractions carry the gate reduction without a key Gram
 // matrix ("Gram elimination for scalar-gate gradients"). Then the chain rule
 // and the reverse in-chunk cumsum of the log-gate gradient ("Complete
-// Reverse Execution and Boundaries", steps 3-4). Per-channel chunks whose
-// gate range needs sub-chunk anchoring are left to the CUDA-core consumers.
+// Reverse Execution and Boundaries", steps 3-4). Chunks whose gate range is
+// wider than the single-anchor limit (sub-chunk anchoring for per-channel
+// gates; strong scalar decay, where the log-gate gradient cancels heavily)
+// are left to the fp32 CUDA-core consumers.
 #include "kda_internal.cuh"
 #include "tc.cuh"
 
@@ -306,7 +308,7 @@ __global__ void __launch_bounds__(CT, 1)
     if (n <= 0) return;
     const int H = s.H;
     const size_t ch = (size_t)c * H + h;
-    if (GATE == 2 && f.WIDE[ch]) return;  // sub-chunk anchoring: CUDA-core consumers
+    if (GATE != 0 && f.WIDE[ch]) return;  // wide gate range: fp32 CUDA-core consumers
     const int tok0 = t.chunk_tok0[c];
     const float scale = s.scale;
     const size_t rowstride = (size_t)H * D;
