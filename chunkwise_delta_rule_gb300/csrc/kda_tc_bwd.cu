@@ -69,7 +69,8 @@ constexpr int S_QGT = 32768;    // Q_g^T [128][64] 16 KB
 constexpr int S_WT = 49152;     // W^T  [128][64] 16 KB
 constexpr int B_STG = 65536;
 constexpr int B_LAM = B_STAGE + 2 * B_STG;     // lambda [128] fp32
-constexpr int B_BAR = B_LAM + 512;
+constexpr int B_TST = B_LAM + 512;             // per-warp transpose staging, 4 x 1280 B
+constexpr int B_BAR = B_TST + 4 * 1280;
 constexpr int BSCAN_SMEM = B_BAR + 64 + 1024;
 
 __device__ __forceinline__ void bscan_prefetch(uint32_t stg, const FwdTC& f, size_t ch, int tid) {
@@ -91,7 +92,8 @@ __global__ void __launch_bounds__(ST, 1)
     uint64_t* bar = reinterpret_cast<uint64_t*>(base + B_BAR);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 2);
     const uint32_t sb = tc::smem_u32(base);
-    const int nseq = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5;
+    const int nseq = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    bf16* tst = reinterpret_cast<bf16*>(base + B_TST + warp * 1280);
     const int H = s.H;
     const int vcol = tid;
     const int c0 = t.seq_chunk0[nseq], c1 = t.seq_chunk0[nseq + 1];
@@ -122,27 +124,32 @@ __global__ void __launch_bounds__(ST, 1)
     }
     tc::tmem_wait_st();
 
+    // dO column of this thread for a chunk, as packed bf16 pairs (loads issued early)
+    auto load_do = [&](int cc, uint32_t (&pw)[32]) {
+        const int len = t.chunk_len[cc], tok0 = t.chunk_tok0[cc];
+        const uint16_t* src = reinterpret_cast<const uint16_t*>(dout) + ((size_t)tok0 * H + h) * D + vcol;
+#pragma unroll
+        for (int i = 0; i < BT; i += 2) {
+            const uint32_t x0 = (i < len) ? src[(size_t)i * H * D] : 0u;
+            const uint32_t x1 = (i + 1 < len) ? src[(size_t)(i + 1) * H * D] : 0u;
+            pw[i / 2] = x0 | (x1 << 16);
+        }
+    };
+    uint32_t dnext[32];
+    if (c0 < c1) load_do(c1 - 1, dnext);
+
     uint32_t ph0 = 0, ph1 = 0;
     bool ok = true;
     for (int c = c1 - 1; c >= c0 && ok; --c) {
         const int it = c1 - 1 - c, stage = it & 1;
         const size_t ch = (size_t)c * H + h;
-        const int len = t.chunk_len[c], tok0 = t.chunk_tok0[c];
         const uint32_t stg = sb + B_STAGE + stage * B_STG;
         sLam[tid] = exp2f(f.GL[ch * D + tid]);
-        // dO^T row of this value column
-        {
-            uint4 pk[8];
-            uint32_t* pw = reinterpret_cast<uint32_t*>(pk);
+        // dO^T row of this value column (loaded during the previous chunk)
 #pragma unroll
-            for (int i = 0; i < BT; i += 2) {
-                const float x0 = (i < len) ? __bfloat162float(dout[((size_t)(tok0 + i) * H + h) * D + vcol]) : 0.f;
-                const float x1 = (i + 1 < len) ? __bfloat162float(dout[((size_t)(tok0 + i + 1) * H + h) * D + vcol]) : 0.f;
-                pw[i / 2] = tc::pack_bf16(x0, x1);
-            }
-#pragma unroll
-            for (int q = 0; q < 8; ++q) *reinterpret_cast<uint4*>(base + B_ADO + tc::sw128_off(D, vcol, q * 16)) = pk[q];
-        }
+        for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<uint4*>(base + B_ADO + tc::sw128_off(D, vcol, q * 16)) =
+                make_uint4(dnext[4 * q], dnext[4 * q + 1], dnext[4 * q + 2], dnext[4 * q + 3]);
         __syncthreads();
         // S+bar^T -> bf16 operand and HBM; then S_bar^T <- S+bar^T diag(lambda)
         bf16* SBP = b.SBP + ch * D * D;
@@ -157,8 +164,7 @@ __global__ void __launch_bounds__(ST, 1)
             for (int jj = 0; jj < 8; ++jj) pw[jj] = tc::pack_bf16(a[2 * jj], a[2 * jj + 1]);
             *reinterpret_cast<uint4*>(base + B_ASB + tc::sw128_off(D, vcol, cb * 2)) = pk[0];
             *reinterpret_cast<uint4*>(base + B_ASB + tc::sw128_off(D, vcol, cb * 2 + 16)) = pk[1];
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj) SBP[(size_t)(cb + jj) * D + vcol] = __float2bfloat16_rn(a[jj]);
+            tc::warp_store_t16(tst, a, SBP + (size_t)cb * D + 32 * warp, D, 16, lane);
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) a[jj] *= sLam[cb + jj];
             tc::tmem_st16(tl + cb, a);
@@ -220,6 +226,7 @@ __global__ void __launch_bounds__(ST, 1)
                 tc::mma_bf16(tb, tc::sdesc_k(sb + B_ANR, D, ks), tc::sdesc_k(stg + S_WT, D, ks), i128, 1);
             tc::mma_commit(&bar[1]);
         }
+        if (c - 1 >= c0) load_do(c - 1, dnext);
         ok = wait_all(&bar[1], ph1, t.err);
         ph1 ^= 1;
         if (!ok) break;
@@ -230,8 +237,7 @@ __global__ void __launch_bounds__(ST, 1)
             float a[16];
             tc::tmem_ld16(tl + 192 + cb, a);
             tc::tmem_wait_ld();
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj) P[(size_t)(cb + jj) * D + vcol] = __float2bfloat16_rn(a[jj]);
+            tc::warp_store_t16(tst, a, P + (size_t)cb * D + 32 * warp, D, 16, lane);
         }
         tc::fence_before_sync();
         __syncthreads();

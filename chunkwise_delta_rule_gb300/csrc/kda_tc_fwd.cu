@@ -44,6 +44,59 @@ __device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, int32_t
 constexpr int PT = 256;
 constexpr int LG = D + 1;  // padded row stride of fp32 [64 x 128] tiles
 constexpr int LA = BT + 1;
+constexpr int LW = D + 8;   // row stride (bf16) of the staged W tile
+constexpr int LU = D + 4;   // row stride (fp32) of the staged U tile
+constexpr int LQ = BT + 8;  // row stride (bf16) of the staged C_q tile
+
+// Blocked inverse of the unit lower-triangular M = I + L (64 x 64, L strict,
+// fp32): the four 16 x 16 diagonal blocks by forward substitution (4 lanes per
+// column), then the off-diagonal blocks level by level,
+//     A_ij = -A_ii * sum_{m=j}^{i-1} L_im A_mj,
+// the 4 x 4 block merge of the GatedDeltaNet-2 spec transcription (section 2.4).
+__device__ __forceinline__ void blocked_inverse(const float* sL, float* sA, float* sT, int tid) {
+    {
+        const int blk = tid >> 6, col = (tid >> 2) & 15, part = tid & 3;
+        const int o = blk * BC;
+        for (int r = part; r < BT; r += 4) sA[r * LA + o + col] = 0.f;
+        for (int r = part; r < BC; r += 4) sA[(o + r) * LA + o + col] = (r == col) ? 1.f : 0.f;
+        __syncwarp();
+        for (int i = 1; i < BC; ++i) {
+            float acc = 0.f;
+            if (i > col)
+                for (int j = col + part; j < i; j += 4) acc = fmaf(sL[(o + i) * LA + o + j], sA[(o + j) * LA + o + col], acc);
+            acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+            acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+            if (part == 0 && i > col) sA[(o + i) * LA + o + col] = -acc;
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+    for (int lvl = 1; lvl < BT / BC; ++lvl) {
+        const int nb = BT / BC - lvl;  // blocks (i, j = i - lvl) on this level
+        // T_ij = sum_{m=j}^{i-1} L_im A_mj
+        for (int idx = tid; idx < nb * BC * BC; idx += PT) {
+            const int b = idx >> 8, r = (idx >> 4) & 15, cc = idx & 15;
+            const int j = b, i = b + lvl;
+            float acc = 0.f;
+            for (int m = j; m < i; ++m)
+#pragma unroll
+                for (int x = 0; x < BC; ++x)
+                    acc = fmaf(sL[(i * BC + r) * LA + m * BC + x], sA[(m * BC + x) * LA + j * BC + cc], acc);
+            sT[(b * BC + r) * (BC + 1) + cc] = acc;
+        }
+        __syncthreads();
+        // A_ij = -A_ii T_ij
+        for (int idx = tid; idx < nb * BC * BC; idx += PT) {
+            const int b = idx >> 8, r = (idx >> 4) & 15, cc = idx & 15;
+            const int j = b, i = b + lvl;
+            float acc = 0.f;
+#pragma unroll
+            for (int x = 0; x < BC; ++x) acc = fmaf(sA[(i * BC + r) * LA + i * BC + x], sT[(b * BC + x) * (BC + 1) + cc], acc);
+            sA[(i * BC + r) * LA + j * BC + cc] = -acc;
+        }
+        __syncthreads();
+    }
+}
 
 template <int GATE, bool BWD>
 __global__ void __launch_bounds__(PT, 1)
@@ -55,10 +108,12 @@ __global__ void __launch_bounds__(PT, 1)
     unsigned char* R1 = base;             // 64 KB operand region (1024-aligned)
     unsigned char* R2 = R1 + 65536;       // 32 KB operand region
     float* sG = reinterpret_cast<float*>(R2 + 32768);  // [64][129] cumulative log2-decay
-    float* sK = sG + BT * LG;             // [64][129] keys
-    float* sAkk = sK + BT * LG;           // [64][65]
+    bf16* sK = reinterpret_cast<bf16*>(sG + BT * LG);  // [64][128] keys
+    bf16* sQ = sK + BT * D;                             // [64][128] queries
+    float* sAkk = reinterpret_cast<float*>(sQ + BT * D);  // [64][65]
     float* sAi = sAkk + BT * LA;          // [64][65]
-    float* sBeta = sAi + BT * LA;         // [64]
+    float* sT = sAi + BT * LA;            // [3][16][17] merge temporaries
+    float* sBeta = sT + 3 * BC * (BC + 1);  // [64]
     float* sC = sBeta + BT;               // [128] anchor per feature
     uint64_t* bar = reinterpret_cast<uint64_t*>(sC + D);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 1);
@@ -71,19 +126,47 @@ __global__ void __launch_bounds__(PT, 1)
     const size_t ch = (size_t)c * H + h;
     const float scale = s.scale;
 
-    for (int idx = tid; idx < BT * D; idx += PT) {
-        const int r = idx >> 7, col = idx & (D - 1);
-        float kv = 0.f, gv = 0.f;
+    // ---- batched vector loads: k, q, v (bf16, 8 per 16 B), g (fp32, 4 per 16 B)
+    uint4 kr4[4], qr4[4], vr4[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int ci = tid + PT * u, r = ci >> 4, c8 = (ci & 15) * 8;
+        kr4[u] = qr4[u] = vr4[u] = make_uint4(0, 0, 0, 0);
         if (r < n) {
-            const size_t off = ((size_t)(tok0 + r) * H + h) * D + col;
-            kv = bfx(k + off);
-            if (GATE == 2) gv = g[off] * LOG2E;
-            if (GATE == 1) gv = g[(size_t)(tok0 + r) * H + h] * LOG2E;
+            const size_t off = ((size_t)(tok0 + r) * H + h) * D + c8;
+            kr4[u] = __ldg(reinterpret_cast<const uint4*>(k + off));
+            qr4[u] = __ldg(reinterpret_cast<const uint4*>(q + off));
+            vr4[u] = __ldg(reinterpret_cast<const uint4*>(v + off));
         }
-        sK[r * LG + col] = kv;
-        sG[r * LG + col] = gv;
+    }
+    float4 gr4[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const int ci = tid + PT * u, r = ci >> 5, c4 = (ci & 31) * 4;
+        gr4[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (r < n) {
+            if (GATE == 2) gr4[u] = __ldg(reinterpret_cast<const float4*>(g + ((size_t)(tok0 + r) * H + h) * D + c4));
+            if (GATE == 1) {
+                const float x = __ldg(g + (size_t)(tok0 + r) * H + h);
+                gr4[u] = make_float4(x, x, x, x);
+            }
+        }
     }
     if (tid < BT) sBeta[tid] = (tid < n) ? bfx(beta + (size_t)(tok0 + tid) * H + h) : 0.f;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int ci = tid + PT * u, r = ci >> 4, c8 = (ci & 15) * 8;
+        *reinterpret_cast<uint4*>(sK + r * D + c8) = kr4[u];
+        *reinterpret_cast<uint4*>(sQ + r * D + c8) = qr4[u];
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const int ci = tid + PT * u, r = ci >> 5, c4 = (ci & 31) * 4;
+        sG[r * LG + c4] = gr4[u].x * LOG2E;
+        sG[r * LG + c4 + 1] = gr4[u].y * LOG2E;
+        sG[r * LG + c4 + 2] = gr4[u].z * LOG2E;
+        sG[r * LG + c4 + 3] = gr4[u].w * LOG2E;
+    }
     if (tid == 0) {
         tc::mbar_init(bar, 1);
         tc::fence_mbar_init();
@@ -118,29 +201,17 @@ __global__ void __launch_bounds__(PT, 1)
     bool ok = true;
     if (!wide) {
         // a2 operands (tf32): A rows 0..63 beta_i k_i 2^(G_i-c), rows 64..127 s q_i 2^(G_i-c);
-        // B rows j: k_j 2^(c-G_j). Q_g (and its transpose) are written on the way.
-        bf16* QG = f.QG + ch * BT * D;
+        // B rows j: k_j 2^(c-G_j)
         for (int idx = tid; idx < 2 * BT * 32; idx += PT) {
             const int r = idx >> 5, cc = idx & 31, i = r & (BT - 1);
             float4 val;
             float* pv = reinterpret_cast<float*>(&val);
-            if (r < BT) {
+            const bf16* src = (r < BT ? sK : sQ) + i * D + 4 * cc;
+            const float mul = (r < BT) ? sBeta[i] : scale;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int col = 4 * cc + e;
-                    pv[e] = sBeta[i] * sK[i * LG + col] * exp2f(sG[i * LG + col] - sC[col]);
-                }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int col = 4 * cc + e;
-                    const float qv = (i < n) ? bfx(q + ((size_t)(tok0 + i) * H + h) * D + col) : 0.f;
-                    const float gi = sG[i * LG + col];
-                    pv[e] = scale * qv * exp2f(gi - sC[col]);
-                    const float qg = scale * qv * exp2f(gi);
-                    QG[i * D + col] = __float2bfloat16_rn(qg);
-                    if (BWD) f.QGT[ch * BT * D + (size_t)col * BT + i] = __float2bfloat16_rn(qg);
-                }
+            for (int e = 0; e < 4; ++e) {
+                const int col = 4 * cc + e;
+                pv[e] = mul * __bfloat162float(src[e]) * exp2f(sG[i * LG + col] - sC[col]);
             }
             *reinterpret_cast<float4*>(R1 + tc::sw128_off(2 * BT, r, cc * 16)) = val;
         }
@@ -151,7 +222,7 @@ __global__ void __launch_bounds__(PT, 1)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int col = 4 * cc + e;
-                pv[e] = sK[j * LG + col] * exp2f(sC[col] - sG[j * LG + col]);
+                pv[e] = __bfloat162float(sK[j * D + col]) * exp2f(sC[col] - sG[j * LG + col]);
             }
             *reinterpret_cast<float4*>(R2 + tc::sw128_off(BT, j, cc * 16)) = val;
         }
@@ -170,6 +241,7 @@ __global__ void __launch_bounds__(PT, 1)
     }
     if (!wide && ok) {
         tc::fence_after_sync();
+        bf16* sAq = reinterpret_cast<bf16*>(R2 + 16384);  // staged C_q [64][72] (transposed copy)
         // read back [Akk ; Aqk]: warps w and w+4 share lanes 32(w%4).., split the 64 columns
         {
             const int row = 32 * (warp & 3) + lane, cb = (warp >> 2) * 32;
@@ -186,62 +258,47 @@ __global__ void __launch_bounds__(PT, 1)
                 }
             } else {
                 const int i = row - BT;
-                bf16* AQ = f.AQK + ch * BT * BT + (size_t)i * BT + cb;
+                uint32_t pw[16];
 #pragma unroll
                 for (int jj = 0; jj < 32; jj += 2) {
                     const int j = cb + jj;
                     const float x0 = (j <= i && i < n) ? a[jj] : 0.f;
                     const float x1 = (j + 1 <= i && i < n) ? a[jj + 1] : 0.f;
-                    *reinterpret_cast<uint32_t*>(AQ + jj) = tc::pack_bf16(x0, x1);
+                    pw[jj / 2] = tc::pack_bf16(x0, x1);
                     if (BWD) {
-                        f.AQKT[ch * BT * BT + (size_t)j * BT + i] = __float2bfloat16_rn(x0);
-                        f.AQKT[ch * BT * BT + (size_t)(j + 1) * BT + i] = __float2bfloat16_rn(x1);
+                        sAq[i * LQ + j] = __float2bfloat16_rn(x0);
+                        sAq[i * LQ + j + 1] = __float2bfloat16_rn(x1);
                     }
                 }
+                uint4* dst = reinterpret_cast<uint4*>(f.AQK + ch * BT * BT + (size_t)i * BT + cb);
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq) dst[qq] = make_uint4(pw[4 * qq], pw[4 * qq + 1], pw[4 * qq + 2], pw[4 * qq + 3]);
             }
         }
         tc::fence_before_sync();
         __syncthreads();
-        // a3: A = (I + Akk)^-1, four lanes per column
-        {
-            const int col = tid >> 2, part = tid & 3;
-            for (int r = part; r < BT; r += 4) sAi[r * LA + col] = (r == col) ? 1.f : 0.f;
-            __syncwarp();
-            for (int i = 1; i < BT; ++i) {
-                float acc = 0.f;
-                if (i > col)
-                    for (int j = col + part; j < i; j += 4) acc = fmaf(sAkk[i * LA + j], sAi[j * LA + col], acc);
-                acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-                acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-                if (part == 0 && i > col) sAi[i * LA + col] = -acc;
-                __syncwarp();
-            }
-        }
-        __syncthreads();
+        // a3: A = (I + Akk)^-1
+        blocked_inverse(sAkk, sAi, sT, tid);
         // a4 operands (tf32): R1 <- E^T [128 keys][64 tokens], R1+32K <- Z^T [128 values][64 tokens],
         // R2 <- A [64 rows i][64 cols j] (B operand of W^T = E^T A^T, K = j)
         for (int idx = tid; idx < D * 16; idx += PT) {
-            const int kr = idx >> 4, cc = idx & 15;
+            const int kr = idx & (D - 1), cc = idx >> 7;
             float4 val;
             float* pv = reinterpret_cast<float*>(&val);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int j = 4 * cc + e;
-                pv[e] = sBeta[j] * sK[j * LG + kr] * exp2f(sG[j * LG + kr]);
+                pv[e] = sBeta[j] * __bfloat162float(sK[j * D + kr]) * exp2f(sG[j * LG + kr]);
             }
             *reinterpret_cast<float4*>(R1 + tc::sw128_off(D, kr, cc * 16)) = val;
         }
-        for (int idx = tid; idx < BT * 32; idx += PT) {
-            const int j = idx >> 5, vc = (idx & 31) * 4;
-            float vv[4] = {0.f, 0.f, 0.f, 0.f};
-            if (j < n) {
-                const bf16* vp = v + ((size_t)(tok0 + j) * H + h) * D + vc;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) vv[e] = bfx(vp + e);
-            }
+        for (int u = 0; u < 4; ++u) {
+            const int ci = tid + PT * u, j = ci >> 4, c8 = (ci & 15) * 8;
+            const bf16* pv = reinterpret_cast<const bf16*>(&vr4[u]);
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                *reinterpret_cast<float*>(R1 + 32768 + tc::sw128_off(D, vc + e, j * 4)) = sBeta[j] * vv[e];
+            for (int e = 0; e < 8; ++e)
+                *reinterpret_cast<float*>(R1 + 32768 + tc::sw128_off(D, c8 + e, j * 4)) = sBeta[j] * __bfloat162float(pv[e]);
         }
         for (int idx = tid; idx < BT * 16; idx += PT) {
             const int i = idx >> 4, cc = idx & 15;
@@ -264,63 +321,99 @@ __global__ void __launch_bounds__(PT, 1)
             for (int st = 0; st < 8; ++st) tc::mma_tf32(tb + 128, tc::sdesc_k(a1, D, st), tc::sdesc_k(b0, BT, st), id, st > 0);
             tc::mma_commit(bar);
         }
-        // element-wise outputs while the MMAs run
+        // element-wise outputs while the MMAs run, as 16-byte stores:
+        // Q_g [i][k] (+ Q_g^T), F^T [k][i] (+ F), A^T [j][i], C_q^T, G at the last token
         {
-            bf16* KGT = f.KGT + ch * D * BT;
-            for (int idx = tid; idx < D * BT; idx += PT) {
-                const int kr = idx >> 6, i = idx & (BT - 1);
-                const float gl = sG[(n - 1) * LG + kr];
-                KGT[idx] = __float2bfloat16_rn(sK[i * LG + kr] * exp2f(gl - sG[i * LG + kr]));
+            const float* glr = sG + (n - 1) * LG;
+            for (int idx = tid; idx < BT * 16; idx += PT) {           // rows i, 8 keys per store
+                const int i = idx >> 4, c8 = (idx & 15) * 8;
+                uint32_t pq[4], pk[4];
+#pragma unroll
+                for (int e = 0; e < 8; e += 2) {
+                    const int kk = c8 + e;
+                    const float g0 = sG[i * LG + kk], g1 = sG[i * LG + kk + 1];
+                    pq[e / 2] = tc::pack_bf16(scale * __bfloat162float(sQ[i * D + kk]) * exp2f(g0),
+                                              scale * __bfloat162float(sQ[i * D + kk + 1]) * exp2f(g1));
+                    pk[e / 2] = tc::pack_bf16(__bfloat162float(sK[i * D + kk]) * exp2f(glr[kk] - g0),
+                                              __bfloat162float(sK[i * D + kk + 1]) * exp2f(glr[kk + 1] - g1));
+                }
+                *reinterpret_cast<uint4*>(f.QG + ch * BT * D + (size_t)i * D + c8) = make_uint4(pq[0], pq[1], pq[2], pq[3]);
+                if (BWD) *reinterpret_cast<uint4*>(f.KG + ch * BT * D + (size_t)i * D + c8) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+            for (int idx = tid; idx < D * 8; idx += PT) {             // rows k, 8 tokens per store
+                const int kk = idx >> 3, i8 = (idx & 7) * 8;
+                uint32_t pk[4], pq[4];
+#pragma unroll
+                for (int e = 0; e < 8; e += 2) {
+                    const int i = i8 + e;
+                    const float g0 = sG[i * LG + kk], g1 = sG[(i + 1) * LG + kk];
+                    pk[e / 2] = tc::pack_bf16(__bfloat162float(sK[i * D + kk]) * exp2f(glr[kk] - g0),
+                                              __bfloat162float(sK[(i + 1) * D + kk]) * exp2f(glr[kk] - g1));
+                    if (BWD)
+                        pq[e / 2] = tc::pack_bf16(scale * __bfloat162float(sQ[i * D + kk]) * exp2f(g0),
+                                                  scale * __bfloat162float(sQ[(i + 1) * D + kk]) * exp2f(g1));
+                }
+                *reinterpret_cast<uint4*>(f.KGT + ch * D * BT + (size_t)kk * BT + i8) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                if (BWD) *reinterpret_cast<uint4*>(f.QGT + ch * D * BT + (size_t)kk * BT + i8) = make_uint4(pq[0], pq[1], pq[2], pq[3]);
             }
             if (BWD) {
-                bf16* KG = f.KG + ch * BT * D;
-                for (int idx = tid; idx < BT * D; idx += PT) {
-                    const int i = idx >> 7, kr = idx & (D - 1);
-                    const float gl = sG[(n - 1) * LG + kr];
-                    KG[idx] = __float2bfloat16_rn(sK[i * LG + kr] * exp2f(gl - sG[i * LG + kr]));
-                }
-                bf16* AIT = f.AIT + ch * BT * BT;
-                for (int idx = tid; idx < BT * BT; idx += PT) {
-                    const int j = idx >> 6, i = idx & (BT - 1);
-                    AIT[idx] = __float2bfloat16_rn(sAi[i * LA + j]);
+                for (int idx = tid; idx < BT * 8; idx += PT) {        // rows j of A^T and C_q^T
+                    const int j = idx >> 3, i8 = (idx & 7) * 8;
+                    uint32_t pa[4], pc[4];
+#pragma unroll
+                    for (int e = 0; e < 8; e += 2) {
+                        pa[e / 2] = tc::pack_bf16(sAi[(i8 + e) * LA + j], sAi[(i8 + e + 1) * LA + j]);
+                        pc[e / 2] = (uint32_t)(*reinterpret_cast<const uint16_t*>(&sAq[(i8 + e) * LQ + j])) |
+                                    ((uint32_t)(*reinterpret_cast<const uint16_t*>(&sAq[(i8 + e + 1) * LQ + j])) << 16);
+                    }
+                    *reinterpret_cast<uint4*>(f.AIT + ch * BT * BT + (size_t)j * BT + i8) = make_uint4(pa[0], pa[1], pa[2], pa[3]);
+                    *reinterpret_cast<uint4*>(f.AQKT + ch * BT * BT + (size_t)j * BT + i8) = make_uint4(pc[0], pc[1], pc[2], pc[3]);
                 }
             }
-            if (tid < D) f.GL[ch * D + tid] = sG[(n - 1) * LG + tid];
+            if (tid < D) f.GL[ch * D + tid] = glr[tid];
         }
         ok = wait_all(bar, 1, t.err);
         if (ok) {
             tc::fence_after_sync();
+            bf16* sW = reinterpret_cast<bf16*>(R1);                     // staged W [64][136]
+            float* sU = reinterpret_cast<float*>(R1 + 2 * BT * LW);     // staged U [64][132]
             const int row = 32 * (warp & 3) + lane;
             if (warp < 4) {
-                // W^T row = key `row`: write W[i][row] and, for the backward, W^T[row][i]
-                bf16* W = f.W + ch * BT * D;
-#pragma unroll 1
+                // W^T row = key `row`: W^T[row][i] for the backward, W[i][row] staged
+#pragma unroll
                 for (int cb = 0; cb < BT; cb += 16) {
                     float a[16];
                     tc::tmem_ld16(tc::taddr(tb + 64, 32 * warp, cb), a);
                     tc::tmem_wait_ld();
 #pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) W[(size_t)(cb + jj) * D + row] = __float2bfloat16_rn(a[jj]);
+                    for (int jj = 0; jj < 16; ++jj) sW[(cb + jj) * LW + row] = __float2bfloat16_rn(a[jj]);
                     if (BWD) {
-                        uint4 pk[2];
-                        uint32_t* pw = reinterpret_cast<uint32_t*>(pk);
+                        uint32_t pw[8];
 #pragma unroll
                         for (int jj = 0; jj < 8; ++jj) pw[jj] = tc::pack_bf16(a[2 * jj], a[2 * jj + 1]);
                         uint4* dst = reinterpret_cast<uint4*>(f.WT + ch * D * BT + (size_t)row * BT + cb);
-                        dst[0] = pk[0];
-                        dst[1] = pk[1];
+                        dst[0] = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+                        dst[1] = make_uint4(pw[4], pw[5], pw[6], pw[7]);
                     }
                 }
             } else {
-                float* U = f.U + ch * BT * D;
-#pragma unroll 1
+#pragma unroll
                 for (int cb = 0; cb < BT; cb += 16) {
                     float a[16];
                     tc::tmem_ld16(tc::taddr(tb + 128, 32 * (warp & 3), cb), a);
                     tc::tmem_wait_ld();
 #pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) U[(size_t)(cb + jj) * D + row] = a[jj];
+                    for (int jj = 0; jj < 16; ++jj) sU[(cb + jj) * LU + row] = a[jj];
                 }
+            }
+            __syncthreads();
+            for (int idx = tid; idx < BT * 16; idx += PT) {
+                const int i = idx >> 4, c8 = (idx & 15) * 8;
+                *reinterpret_cast<uint4*>(f.W + ch * BT * D + (size_t)i * D + c8) = *reinterpret_cast<const uint4*>(sW + i * LW + c8);
+            }
+            for (int idx = tid; idx < BT * 32; idx += PT) {
+                const int i = idx >> 5, c4 = (idx & 31) * 4;
+                *reinterpret_cast<float4*>(f.U + ch * BT * D + (size_t)i * D + c4) = *reinterpret_cast<const float4*>(sU + i * LU + c4);
             }
         }
     }
@@ -341,7 +434,9 @@ constexpr int STG_KG = 16384;                // F^T [128][64]  16 KB
 constexpr int STG_QG = 32768;                // Q_g [64][128]  16 KB
 constexpr int STG_AQ = 49152;                // C_q [64][64]    8 KB
 constexpr int STG_BYTES = 57344;
-constexpr int OFF_BAR = OFF_STAGE + 2 * STG_BYTES;
+constexpr int OFF_LAM = OFF_STAGE + 2 * STG_BYTES;   // lambda [128] fp32
+constexpr int OFF_TST = OFF_LAM + 512;                 // per-warp transpose staging, 4 x 1280 B
+constexpr int OFF_BAR = OFF_TST + 4 * 1280;
 constexpr int SCAN_SMEM = OFF_BAR + 64 + 1024;
 
 using tc::cp_async16;
@@ -367,8 +462,10 @@ __global__ void __launch_bounds__(ST, 1)
                                                            ~static_cast<uintptr_t>(1023));
     uint64_t* bar = reinterpret_cast<uint64_t*>(base + OFF_BAR);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 2);
+    float* sLam = reinterpret_cast<float*>(base + OFF_LAM);
     const uint32_t sb = tc::smem_u32(base);
-    const int nseq = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5;
+    const int nseq = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    bf16* tst = reinterpret_cast<bf16*>(base + OFF_TST + warp * 1280);
     const int H = s.H;
     const int vcol = tid;  // TMEM lane and value column of this thread
     const int c0 = t.seq_chunk0[nseq], c1 = t.seq_chunk0[nseq + 1];
@@ -419,7 +516,8 @@ __global__ void __launch_bounds__(ST, 1)
         const int len = t.chunk_len[c], tok0 = t.chunk_tok0[c];
         const uint32_t stg = sb + OFF_STAGE + stage * STG_BYTES;
         // 1. S^T -> bf16 operand (and the saved state), then S^T <- S^T diag(lambda)
-        const float* GL = f.GL + ch * D;
+        sLam[tid] = exp2f(f.GL[ch * D + tid]);
+        __syncthreads();
 #pragma unroll 1
         for (int cb = 0; cb < D; cb += 16) {
             float a[16];
@@ -431,13 +529,9 @@ __global__ void __launch_bounds__(ST, 1)
             for (int jj = 0; jj < 8; ++jj) pw[jj] = tc::pack_bf16(a[2 * jj], a[2 * jj + 1]);
             *reinterpret_cast<uint4*>(base + OFF_AS + tc::sw128_off(D, vcol, cb * 2)) = pk[0];
             *reinterpret_cast<uint4*>(base + OFF_AS + tc::sw128_off(D, vcol, cb * 2 + 16)) = pk[1];
-            if (MODE & 2) {
-                bf16* HS = f.HS + ch * D * D;
+            if (MODE & 2) tc::warp_store_t16(tst, a, f.HS + ch * D * D + (size_t)cb * D + 32 * warp, D, 16, lane);
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) HS[(size_t)(cb + jj) * D + vcol] = __float2bfloat16_rn(a[jj]);
-            }
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj) a[jj] *= exp2f(__ldg(GL + cb + jj));
+            for (int jj = 0; jj < 16; ++jj) a[jj] *= sLam[cb + jj];
             tc::tmem_st16(tl + cb, a);
         }
         tc::tmem_wait_st();
@@ -495,11 +589,7 @@ __global__ void __launch_bounds__(ST, 1)
             for (int jj = 0; jj < 8; ++jj) pw[jj] = tc::pack_bf16(a[2 * jj], a[2 * jj + 1]);
             *reinterpret_cast<uint4*>(base + OFF_AR + tc::sw128_off(D, vcol, cb * 2)) = pk[0];
             *reinterpret_cast<uint4*>(base + OFF_AR + tc::sw128_off(D, vcol, cb * 2 + 16)) = pk[1];
-            if (MODE & 2) {
-                bf16* Rg = f.R + ch * BT * D;
-#pragma unroll
-                for (int jj = 0; jj < 16; ++jj) Rg[(size_t)(cb + jj) * D + vcol] = __float2bfloat16_rn(a[jj]);
-            }
+            if (MODE & 2) tc::warp_store_t16(tst, a, f.R + ch * BT * D + (size_t)cb * D + 32 * warp, D, 16, lane);
         }
         tc::fence_async_smem();
         tc::fence_before_sync();
@@ -526,12 +616,12 @@ __global__ void __launch_bounds__(ST, 1)
         if (MODE & 1) {
 #pragma unroll 1
             for (int cb = 0; cb < BT; cb += 16) {
+                if (cb >= len) break;
                 float a[16];
                 tc::tmem_ld16(tl + 192 + cb, a);
                 tc::tmem_wait_ld();
-#pragma unroll
-                for (int jj = 0; jj < 16; ++jj)
-                    if (cb + jj < len) o[((size_t)(tok0 + cb + jj) * H + h) * D + vcol] = __float2bfloat16_rn(a[jj]);
+                tc::warp_store_t16(tst, a, o + ((size_t)(tok0 + cb) * H + h) * D + 32 * warp, (size_t)H * D,
+                                   len - cb, lane);
             }
         }
         tc::fence_before_sync();
@@ -554,7 +644,8 @@ __global__ void __launch_bounds__(ST, 1)
     if (warp == 0) tc::tmem_dealloc(tb, 256);
 }
 
-constexpr size_t PREP_SMEM = 65536 + 32768 + sizeof(float) * (2 * BT * LG + 2 * BT * LA + BT + D) + 64 + 1024;
+constexpr size_t PREP_SMEM = 65536 + 32768 + sizeof(float) * (BT * LG + 2 * BT * LA + 3 * BC * (BC + 1) + BT + D) +
+                             2 * 2 * BT * D + 64 + 1024;
 
 template <int GATE, bool BWD>
 cudaError_t run_prep(const Shape& s, const void* q, const void* k, const void* v, const void* beta,

@@ -193,6 +193,24 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
+// A warp holds a 32-row x 16-column block of an M = 128 accumulator (lane t:
+// row t, a[0..15]). Writes its transpose, dst[c * ld + t] for c < ncols rows
+// of the destination, as 16-byte stores through a per-warp staging tile of
+// 16 x 40 bf16.
+__device__ __forceinline__ void warp_store_t16(__nv_bfloat16* stg, const float (&a)[16], __nv_bfloat16* dst,
+                                               size_t ld, int ncols, int lane) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) stg[j * 40 + lane] = __float2bfloat16_rn(a[j]);
+    __syncwarp();
+#pragma unroll
+    for (int p = lane; p < 64; p += 32) {
+        const int r = p >> 2, q = p & 3;
+        if (r < ncols)
+            *reinterpret_cast<uint4*>(dst + (size_t)r * ld + q * 8) = *reinterpret_cast<const uint4*>(stg + r * 40 + q * 8);
+    }
+    __syncwarp();
+}
+
 // bf16 pair packing
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 t = __floats2bfloat162_rn(lo, hi);
