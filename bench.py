@@ -33,6 +33,22 @@ BT = 64
 WORKLOAD_IDX = 4
 
 
+def heads_subset(case, H):
+    """The same workload restricted to its first H heads (profiling captures
+    of a smaller device footprint)."""
+    from workloads import Case
+
+    def sl(x):
+        return None if x is None else x[:, :, :H].contiguous()
+
+    def st(x):
+        return None if x is None else x[:, :H].contiguous()
+
+    return Case(case.io, case.gate, case.B, case.T, H, case.K, case.V, case.scale, sl(case.q), sl(case.k),
+                sl(case.v), sl(case.beta), sl(case.g), st(case.h0), sl(case.do), st(case.dht),
+                case.cu_seqlens, case.name + f"_h{H}", dict(case.meta))
+
+
 # ---------------------------------------------------------------- FLOP model
 def chunk_lengths(case):
     out = []
@@ -218,6 +234,8 @@ def run_ours(args):
     torch.cuda.set_device(dev)
     cfg = CONFIGS[args.config]
     case_cpu = make_config_case(args.config)
+    if args.heads:
+        case_cpu = heads_subset(case_cpu, args.heads)
     case = case_cpu.to(dev)
     lib = _lib.load()
     p = kda.make_problem(case.q, case.k, case.v, case.g, case.beta, gate=case.gate,
@@ -318,7 +336,7 @@ def run_ours(args):
             "steps": K, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if cfg["io"] == "bf16" else "fp32",
             "data": "synthetic (seeded; shapes and distributions of the workload)",
-            "config": {"workload": cfg["name"], "B": case.B, "T": case.T, "H": case.H, "dk": case.K,
+            "config": {"workload": cfg["name"] + (f"_first{case.H}heads" if args.heads else ""), "B": case.B, "T": case.T, "H": case.H, "dk": case.K,
                        "dv": case.V, "gate": case.gate, "io": cfg["io"], "chunk": BT,
                        "policy": "recompute", "parallelism": f"replicas x{ws}",
                        "l2": "flushed by a 256 MiB write before every timed step"},
@@ -456,6 +474,7 @@ def main():
     ap.add_argument("--config", type=int, default=WORKLOAD_IDX)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--heads", type=int, default=0, help="restrict the workload to its first H heads (profiling)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
