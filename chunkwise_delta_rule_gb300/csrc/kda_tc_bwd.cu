@@ -56,7 +56,7 @@ __device__ __forceinline__ void load_tile(uint32_t sbase, const bf16* src, size_
 }
 
 // ====================================================== k_bwd_scan_tc
-constexpr int ST = 128;
+constexpr int ST = 256;         // 8 warps: warps w and w+4 share lane quarter w%4, split columns
 constexpr int B_ASB = 0;        // S+bar^T bf16 [128][128] 32 KB
 constexpr int B_ADO = 32768;    // dO^T    bf16 [128][64]  16 KB
 constexpr int B_ARB = 49152;    // R_bar^T bf16 [128][64]  16 KB
@@ -69,8 +69,8 @@ constexpr int S_QGT = 32768;    // Q_g^T [128][64] 16 KB
 constexpr int S_WT = 49152;     // W^T  [128][64] 16 KB
 constexpr int B_STG = 65536;
 constexpr int B_LAM = B_STAGE + 2 * B_STG;     // lambda [128] fp32
-constexpr int B_TST = B_LAM + 512;             // per-warp transpose staging, 4 x 1280 B
-constexpr int B_BAR = B_TST + 4 * 1280;
+constexpr int B_TST = B_LAM + 512;             // per-warp transpose staging, 8 x 1280 B
+constexpr int B_BAR = B_TST + 8 * 1280;
 constexpr int BSCAN_SMEM = B_BAR + 64 + 1024;
 
 __device__ __forceinline__ void bscan_prefetch(uint32_t stg, const FwdTC& f, size_t ch, int tid) {
@@ -90,17 +90,20 @@ __global__ void __launch_bounds__(ST, 1)
                                                            ~static_cast<uintptr_t>(1023));
     float* sLam = reinterpret_cast<float*>(base + B_LAM);
     uint64_t* bar = reinterpret_cast<uint64_t*>(base + B_BAR);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 2);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 3);
     const uint32_t sb = tc::smem_u32(base);
     const int nseq = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quad = warp & 3, half = warp >> 2;
     bf16* tst = reinterpret_cast<bf16*>(base + B_TST + warp * 1280);
     const int H = s.H;
-    const int vcol = tid;
+    const int vcol = 32 * quad + lane;
+    const int kb = 64 * half, ib = 32 * half;
     const int c0 = t.seq_chunk0[nseq], c1 = t.seq_chunk0[nseq + 1];
 
     if (tid == 0) {
         tc::mbar_init(&bar[0], 1);
         tc::mbar_init(&bar[1], 1);
+        tc::mbar_init(&bar[2], 1);
         tc::fence_mbar_init();
     }
     if (warp == 0) {
@@ -112,11 +115,11 @@ __global__ void __launch_bounds__(ST, 1)
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tb = *tslot;
-    const uint32_t tl = tc::taddr(tb, 32 * warp, 0);
+    const uint32_t tl = tc::taddr(tb, 32 * quad, 0);
     const size_t st_off = ((size_t)nseq * H + h) * D * D;
 
 #pragma unroll 1
-    for (int cb = 0; cb < D; cb += 16) {
+    for (int cb = kb; cb < kb + 64; cb += 16) {
         float a[16];
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) a[jj] = dht ? dht[st_off + (size_t)(cb + jj) * D + vcol] : 0.f;
@@ -124,47 +127,46 @@ __global__ void __launch_bounds__(ST, 1)
     }
     tc::tmem_wait_st();
 
-    // dO column of this thread for a chunk, as packed bf16 pairs (loads issued early)
-    auto load_do = [&](int cc, uint32_t (&pw)[32]) {
+    // this thread's half of the dO column of a chunk, as packed bf16 pairs (loads issued early)
+    auto load_do = [&](int cc, uint32_t (&pw)[16]) {
         const int len = t.chunk_len[cc], tok0 = t.chunk_tok0[cc];
-        const uint16_t* src = reinterpret_cast<const uint16_t*>(dout) + ((size_t)tok0 * H + h) * D + vcol;
+        const uint16_t* src = reinterpret_cast<const uint16_t*>(dout) + ((size_t)(tok0 + ib) * H + h) * D + vcol;
 #pragma unroll
-        for (int i = 0; i < BT; i += 2) {
-            const uint32_t x0 = (i < len) ? src[(size_t)i * H * D] : 0u;
-            const uint32_t x1 = (i + 1 < len) ? src[(size_t)(i + 1) * H * D] : 0u;
+        for (int i = 0; i < 32; i += 2) {
+            const uint32_t x0 = (ib + i < len) ? src[(size_t)i * H * D] : 0u;
+            const uint32_t x1 = (ib + i + 1 < len) ? src[(size_t)(i + 1) * H * D] : 0u;
             pw[i / 2] = x0 | (x1 << 16);
         }
     };
-    uint32_t dnext[32];
+    uint32_t dnext[16];
     if (c0 < c1) load_do(c1 - 1, dnext);
 
-    uint32_t ph0 = 0, ph1 = 0;
+    uint32_t ph0 = 0, ph1 = 0, ph2 = 0;
     bool ok = true;
     for (int c = c1 - 1; c >= c0 && ok; --c) {
         const int it = c1 - 1 - c, stage = it & 1;
         const size_t ch = (size_t)c * H + h;
         const uint32_t stg = sb + B_STAGE + stage * B_STG;
-        sLam[tid] = exp2f(f.GL[ch * D + tid]);
+        if (tid < D) sLam[tid] = exp2f(f.GL[ch * D + tid]);
         // dO^T row of this value column (loaded during the previous chunk)
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-            *reinterpret_cast<uint4*>(base + B_ADO + tc::sw128_off(D, vcol, q * 16)) =
+        for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4*>(base + B_ADO + tc::sw128_off(D, vcol, ib * 2 + q * 16)) =
                 make_uint4(dnext[4 * q], dnext[4 * q + 1], dnext[4 * q + 2], dnext[4 * q + 3]);
         __syncthreads();
         // S+bar^T -> bf16 operand and HBM; then S_bar^T <- S+bar^T diag(lambda)
         bf16* SBP = b.SBP + ch * D * D;
 #pragma unroll 1
-        for (int cb = 0; cb < D; cb += 16) {
+        for (int cb = kb; cb < kb + 64; cb += 16) {
             float a[16];
             tc::tmem_ld16(tl + cb, a);
             tc::tmem_wait_ld();
-            uint4 pk[2];
-            uint32_t* pw = reinterpret_cast<uint32_t*>(pk);
+            uint32_t pw[8];
 #pragma unroll
             for (int jj = 0; jj < 8; ++jj) pw[jj] = tc::pack_bf16(a[2 * jj], a[2 * jj + 1]);
-            *reinterpret_cast<uint4*>(base + B_ASB + tc::sw128_off(D, vcol, cb * 2)) = pk[0];
-            *reinterpret_cast<uint4*>(base + B_ASB + tc::sw128_off(D, vcol, cb * 2 + 16)) = pk[1];
-            tc::warp_store_t16(tst, a, SBP + (size_t)cb * D + 32 * warp, D, 16, lane);
+            *reinterpret_cast<uint4*>(base + B_ASB + tc::sw128_off(D, vcol, cb * 2)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+            *reinterpret_cast<uint4*>(base + B_ASB + tc::sw128_off(D, vcol, cb * 2 + 16)) = make_uint4(pw[4], pw[5], pw[6], pw[7]);
+            tc::warp_store_t16(tst, a, SBP + (size_t)cb * D + 32 * quad, D, 16, lane);
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) a[jj] *= sLam[cb + jj];
             tc::tmem_st16(tl + cb, a);
@@ -183,34 +185,33 @@ __global__ void __launch_bounds__(ST, 1)
 #pragma unroll 1
             for (int ks = 0; ks < 4; ++ks)
                 tc::mma_bf16(tb + 128, tc::sdesc_k(sb + B_ADO, D, ks), tc::sdesc_k(stg + S_AQT, BT, ks), i64, 1);
+            tc::mma_commit(&bar[0]);
 #pragma unroll 1
             for (int ks = 0; ks < 4; ++ks)
                 tc::mma_bf16(tb, tc::sdesc_k(sb + B_ADO, D, ks), tc::sdesc_k(stg + S_QGT, D, ks), i128, 1);
-            tc::mma_commit(&bar[0]);
         }
         if (c - 1 >= c0) bscan_prefetch(sb + B_STAGE + (stage ^ 1) * B_STG, f, (size_t)(c - 1) * H + h, tid);
         ok = wait_all(&bar[0], ph0, t.err);
         ph0 ^= 1;
         if (!ok) break;
         tc::fence_after_sync();
-        // R_bar^T -> bf16 operands (and its negation)
+        // R_bar^T -> bf16 operands (and its negation), this thread's half of the rows
 #pragma unroll
-        for (int cb = 0; cb < BT; cb += 16) {
+        for (int cq = 0; cq < 32; cq += 16) {
             float a[16];
-            tc::tmem_ld16(tl + 128 + cb, a);
+            tc::tmem_ld16(tl + 128 + ib + cq, a);
             tc::tmem_wait_ld();
-            uint4 pk[2], nk[2];
-            uint32_t* pw = reinterpret_cast<uint32_t*>(pk);
-            uint32_t* nw = reinterpret_cast<uint32_t*>(nk);
+            uint32_t pw[8], nw[8];
 #pragma unroll
             for (int jj = 0; jj < 8; ++jj) {
                 pw[jj] = tc::pack_bf16(a[2 * jj], a[2 * jj + 1]);
                 nw[jj] = tc::pack_bf16(-a[2 * jj], -a[2 * jj + 1]);
             }
-            *reinterpret_cast<uint4*>(base + B_ARB + tc::sw128_off(D, vcol, cb * 2)) = pk[0];
-            *reinterpret_cast<uint4*>(base + B_ARB + tc::sw128_off(D, vcol, cb * 2 + 16)) = pk[1];
-            *reinterpret_cast<uint4*>(base + B_ANR + tc::sw128_off(D, vcol, cb * 2)) = nk[0];
-            *reinterpret_cast<uint4*>(base + B_ANR + tc::sw128_off(D, vcol, cb * 2 + 16)) = nk[1];
+            const int bo = (ib + cq) * 2;
+            *reinterpret_cast<uint4*>(base + B_ARB + tc::sw128_off(D, vcol, bo)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+            *reinterpret_cast<uint4*>(base + B_ARB + tc::sw128_off(D, vcol, bo + 16)) = make_uint4(pw[4], pw[5], pw[6], pw[7]);
+            *reinterpret_cast<uint4*>(base + B_ANR + tc::sw128_off(D, vcol, bo)) = make_uint4(nw[0], nw[1], nw[2], nw[3]);
+            *reinterpret_cast<uint4*>(base + B_ANR + tc::sw128_off(D, vcol, bo + 16)) = make_uint4(nw[4], nw[5], nw[6], nw[7]);
         }
         tc::fence_async_smem();
         tc::fence_before_sync();
@@ -221,31 +222,35 @@ __global__ void __launch_bounds__(ST, 1)
 #pragma unroll 1
             for (int ks = 0; ks < 4; ++ks)
                 tc::mma_bf16(tb + 192, tc::sdesc_k(sb + B_ARB, D, ks), tc::sdesc_k(stg + S_AIT, BT, ks), i64, ks > 0);
+            tc::mma_commit(&bar[2]);
 #pragma unroll 1
             for (int ks = 0; ks < 4; ++ks)
                 tc::mma_bf16(tb, tc::sdesc_k(sb + B_ANR, D, ks), tc::sdesc_k(stg + S_WT, D, ks), i128, 1);
             tc::mma_commit(&bar[1]);
         }
         if (c - 1 >= c0) load_do(c - 1, dnext);
-        ok = wait_all(&bar[1], ph1, t.err);
-        ph1 ^= 1;
+        ok = wait_all(&bar[2], ph2, t.err);
+        ph2 ^= 1;
         if (!ok) break;
         tc::fence_after_sync();
         bf16* P = b.P + ch * BT * D;
 #pragma unroll 1
-        for (int cb = 0; cb < BT; cb += 16) {
+        for (int cq = 0; cq < 32; cq += 16) {
             float a[16];
-            tc::tmem_ld16(tl + 192 + cb, a);
+            tc::tmem_ld16(tl + 192 + ib + cq, a);
             tc::tmem_wait_ld();
-            tc::warp_store_t16(tst, a, P + (size_t)cb * D + 32 * warp, D, 16, lane);
+            tc::warp_store_t16(tst, a, P + (size_t)(ib + cq) * D + 32 * quad, D, 16, lane);
         }
         tc::fence_before_sync();
-        __syncthreads();
+        ok = wait_all(&bar[1], ph1, t.err);
+        ph1 ^= 1;
+        if (!ok) break;
+        tc::fence_after_sync();
     }
     if (ok && dh0) {
         tc::fence_after_sync();
 #pragma unroll 1
-        for (int cb = 0; cb < D; cb += 16) {
+        for (int cb = kb; cb < kb + 64; cb += 16) {
             float a[16];
             tc::tmem_ld16(tl + cb, a);
             tc::tmem_wait_ld();

@@ -423,7 +423,7 @@ __global__ void __launch_bounds__(PT, 1)
 }
 
 // ======================================================= k_fwd_scan_tc
-constexpr int ST = 128;  // threads: one per value column / TMEM lane
+constexpr int ST = 256;  // 8 warps: warps w and w+4 share TMEM lane quarter w%4 and split columns
 
 // Shared-memory map (bytes from the 1024-aligned base).
 constexpr int OFF_AS = 0;                    // S^T bf16 [128][128]   32 KB
@@ -435,8 +435,8 @@ constexpr int STG_QG = 32768;                // Q_g [64][128]  16 KB
 constexpr int STG_AQ = 49152;                // C_q [64][64]    8 KB
 constexpr int STG_BYTES = 57344;
 constexpr int OFF_LAM = OFF_STAGE + 2 * STG_BYTES;   // lambda [128] fp32
-constexpr int OFF_TST = OFF_LAM + 512;                 // per-warp transpose staging, 4 x 1280 B
-constexpr int OFF_BAR = OFF_TST + 4 * 1280;
+constexpr int OFF_TST = OFF_LAM + 512;                 // per-warp transpose staging, 8 x 1280 B
+constexpr int OFF_BAR = OFF_TST + 8 * 1280;
 constexpr int SCAN_SMEM = OFF_BAR + 64 + 1024;
 
 using tc::cp_async16;
@@ -454,6 +454,17 @@ __device__ __forceinline__ void load_tile(uint32_t sbase, const bf16* src, int t
 }
 
 template <int MODE>
+__device__ __forceinline__ void fscan_prefetch(uint32_t stg, const FwdTC& f, size_t ch, int tid) {
+    load_tile<BT, D>(stg + STG_W, f.W + ch * BT * D, tid);
+    load_tile<D, BT>(stg + STG_KG, f.KGT + ch * D * BT, tid);
+    if (MODE & 1) {
+        load_tile<BT, D>(stg + STG_QG, f.QG + ch * BT * D, tid);
+        load_tile<BT, BT>(stg + STG_AQ, f.AQK + ch * BT * BT, tid);
+    }
+    cp_async_commit();
+}
+
+template <int MODE>
 __global__ void __launch_bounds__(ST, 1)
     k_fwd_scan_tc(Shape s, const float* __restrict__ h0, Table t, FwdTC f, bf16* __restrict__ o,
                   float* __restrict__ ht) {
@@ -461,46 +472,39 @@ __global__ void __launch_bounds__(ST, 1)
     unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                            ~static_cast<uintptr_t>(1023));
     uint64_t* bar = reinterpret_cast<uint64_t*>(base + OFF_BAR);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 2);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 3);
     float* sLam = reinterpret_cast<float*>(base + OFF_LAM);
     const uint32_t sb = tc::smem_u32(base);
     const int nseq = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quad = warp & 3, half = warp >> 2;
     bf16* tst = reinterpret_cast<bf16*>(base + OFF_TST + warp * 1280);
     const int H = s.H;
-    const int vcol = tid;  // TMEM lane and value column of this thread
+    const int vcol = 32 * quad + lane;  // TMEM lane and value column of this thread
     const int c0 = t.seq_chunk0[nseq], c1 = t.seq_chunk0[nseq + 1];
 
     if (tid == 0) {
         tc::mbar_init(&bar[0], 1);
         tc::mbar_init(&bar[1], 1);
+        tc::mbar_init(&bar[2], 1);
         tc::fence_mbar_init();
     }
     if (warp == 0) {
         tc::tmem_alloc(tslot, 256);
         tc::tmem_relinquish();
     }
-    // prefetch the first chunk's operands
-    if (c0 < c1) {
-        const size_t ch = (size_t)c0 * H + h;
-        const uint32_t stg = sb + OFF_STAGE;
-        load_tile<BT, D>(stg + STG_W, f.W + ch * BT * D, tid);
-        load_tile<D, BT>(stg + STG_KG, f.KGT + ch * D * BT, tid);
-        if (MODE & 1) {
-            load_tile<BT, D>(stg + STG_QG, f.QG + ch * BT * D, tid);
-            load_tile<BT, BT>(stg + STG_AQ, f.AQK + ch * BT * BT, tid);
-        }
-        cp_async_commit();
-    }
+    if (c0 < c1) fscan_prefetch<MODE>(sb + OFF_STAGE, f, (size_t)c0 * H + h, tid);
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tb = *tslot;
-    const uint32_t tl = tc::taddr(tb, 32 * warp, 0);  // this warp's lane quarter
+    const uint32_t tl = tc::taddr(tb, 32 * quad, 0);  // this warp's lane quarter
     const size_t st_off = ((size_t)nseq * H + h) * D * D;
+    const int kb = 64 * half;   // this thread's half of the key columns of S^T
+    const int ib = 32 * half;   // this thread's half of the chunk rows
 
-    // S^T <- h0^T (thread v holds row v: h0[k][v] for all k)
+    // S^T <- h0^T (thread holds row v: h0[k][v] for its keys)
 #pragma unroll 1
-    for (int cb = 0; cb < D; cb += 16) {
+    for (int cb = kb; cb < kb + 64; cb += 16) {
         float a[16];
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) a[jj] = h0 ? h0[st_off + (size_t)(cb + jj) * D + vcol] : 0.f;
@@ -508,43 +512,42 @@ __global__ void __launch_bounds__(ST, 1)
     }
     tc::tmem_wait_st();
 
-    uint32_t ph0 = 0, ph1 = 0;
+    uint32_t ph0 = 0, ph1 = 0, ph2 = 0;
     bool ok = true;
     for (int c = c0; c < c1 && ok; ++c) {
         const int it = c - c0, stage = it & 1;
         const size_t ch = (size_t)c * H + h;
         const int len = t.chunk_len[c], tok0 = t.chunk_tok0[c];
         const uint32_t stg = sb + OFF_STAGE + stage * STG_BYTES;
-        // 1. S^T -> bf16 operand (and the saved state), then S^T <- S^T diag(lambda)
-        sLam[tid] = exp2f(f.GL[ch * D + tid]);
+        // U rows of this thread's value column (consumed after the first MMA)
+        float u[32];
+        const float* U = f.U + ch * BT * D + (size_t)ib * D + vcol;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) u[i] = U[(size_t)i * D];
+        if (tid < D) sLam[tid] = exp2f(f.GL[ch * D + tid]);
         __syncthreads();
+        // 1. S^T -> bf16 operand (and the saved state), then S^T <- S^T diag(lambda)
 #pragma unroll 1
-        for (int cb = 0; cb < D; cb += 16) {
+        for (int cb = kb; cb < kb + 64; cb += 16) {
             float a[16];
             tc::tmem_ld16(tl + cb, a);
             tc::tmem_wait_ld();
-            uint4 pk[2];
-            uint32_t* pw = reinterpret_cast<uint32_t*>(pk);
+            uint32_t pw[8];
 #pragma unroll
             for (int jj = 0; jj < 8; ++jj) pw[jj] = tc::pack_bf16(a[2 * jj], a[2 * jj + 1]);
-            *reinterpret_cast<uint4*>(base + OFF_AS + tc::sw128_off(D, vcol, cb * 2)) = pk[0];
-            *reinterpret_cast<uint4*>(base + OFF_AS + tc::sw128_off(D, vcol, cb * 2 + 16)) = pk[1];
-            if (MODE & 2) tc::warp_store_t16(tst, a, f.HS + ch * D * D + (size_t)cb * D + 32 * warp, D, 16, lane);
+            *reinterpret_cast<uint4*>(base + OFF_AS + tc::sw128_off(D, vcol, cb * 2)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+            *reinterpret_cast<uint4*>(base + OFF_AS + tc::sw128_off(D, vcol, cb * 2 + 16)) = make_uint4(pw[4], pw[5], pw[6], pw[7]);
+            if (MODE & 2) tc::warp_store_t16(tst, a, f.HS + ch * D * D + (size_t)cb * D + 32 * quad, D, 16, lane);
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) a[jj] *= sLam[cb + jj];
             tc::tmem_st16(tl + cb, a);
         }
         tc::tmem_wait_st();
-        // 2. U column of this thread
-        float u[BT];
-        const float* U = f.U + ch * BT * D;
-#pragma unroll
-        for (int i = 0; i < BT; ++i) u[i] = U[(size_t)i * D + vcol];
         cp_async_wait_all();
         tc::fence_async_smem();
         tc::fence_before_sync();
         __syncthreads();
-        // 3. D1 = S^T W^T ; O^T = S^T Q_g^T
+        // 2. D1 = S^T W^T ; O^T = S^T Q_g^T
         if (tid == 0) {
             tc::fence_after_sync();
             const uint32_t id = tc::idesc_bf16(128, 64);
@@ -552,85 +555,80 @@ __global__ void __launch_bounds__(ST, 1)
 #pragma unroll 1
             for (int ks = 0; ks < 8; ++ks)
                 tc::mma_bf16(tb + 128, tc::sdesc_k(aS, D, ks), tc::sdesc_k(stg + STG_W, BT, ks), id, ks > 0);
+            tc::mma_commit(&bar[0]);
             if (MODE & 1) {
 #pragma unroll 1
                 for (int ks = 0; ks < 8; ++ks)
                     tc::mma_bf16(tb + 192, tc::sdesc_k(aS, D, ks), tc::sdesc_k(stg + STG_QG, BT, ks), id, ks > 0);
             }
-            tc::mma_commit(&bar[0]);
         }
         // prefetch chunk c+1 into the other stage (its previous MMAs have completed)
-        if (c + 1 < c1) {
-            const size_t ch1 = (size_t)(c + 1) * H + h;
-            const uint32_t stn = sb + OFF_STAGE + (stage ^ 1) * STG_BYTES;
-            load_tile<BT, D>(stn + STG_W, f.W + ch1 * BT * D, tid);
-            load_tile<D, BT>(stn + STG_KG, f.KGT + ch1 * D * BT, tid);
-            if (MODE & 1) {
-                load_tile<BT, D>(stn + STG_QG, f.QG + ch1 * BT * D, tid);
-                load_tile<BT, BT>(stn + STG_AQ, f.AQK + ch1 * BT * BT, tid);
-            }
-            cp_async_commit();
-        }
+        if (c + 1 < c1) fscan_prefetch<MODE>(sb + OFF_STAGE + (stage ^ 1) * STG_BYTES, f, (size_t)(c + 1) * H + h, tid);
         ok = wait_all(&bar[0], ph0, t.err);
         ph0 ^= 1;
         if (!ok) break;
         tc::fence_after_sync();
-        // 4. R^T = U^T - D1 (bf16 operand; saved for the backward)
+        // 3. R^T = U^T - D1 (bf16 operand; saved for the backward)
 #pragma unroll
-        for (int cb = 0; cb < BT; cb += 16) {
+        for (int cq = 0; cq < 32; cq += 16) {
             float a[16];
-            tc::tmem_ld16(tl + 128 + cb, a);
+            tc::tmem_ld16(tl + 128 + ib + cq, a);
             tc::tmem_wait_ld();
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) a[jj] = u[cb + jj] - a[jj];
-            uint4 pk[2];
-            uint32_t* pw = reinterpret_cast<uint32_t*>(pk);
+            for (int jj = 0; jj < 16; ++jj) a[jj] = u[cq + jj] - a[jj];
+            uint32_t pw[8];
 #pragma unroll
             for (int jj = 0; jj < 8; ++jj) pw[jj] = tc::pack_bf16(a[2 * jj], a[2 * jj + 1]);
-            *reinterpret_cast<uint4*>(base + OFF_AR + tc::sw128_off(D, vcol, cb * 2)) = pk[0];
-            *reinterpret_cast<uint4*>(base + OFF_AR + tc::sw128_off(D, vcol, cb * 2 + 16)) = pk[1];
-            if (MODE & 2) tc::warp_store_t16(tst, a, f.R + ch * BT * D + (size_t)cb * D + 32 * warp, D, 16, lane);
+            *reinterpret_cast<uint4*>(base + OFF_AR + tc::sw128_off(D, vcol, (ib + cq) * 2)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+            *reinterpret_cast<uint4*>(base + OFF_AR + tc::sw128_off(D, vcol, (ib + cq) * 2 + 16)) = make_uint4(pw[4], pw[5], pw[6], pw[7]);
+            if (MODE & 2) tc::warp_store_t16(tst, a, f.R + ch * BT * D + (size_t)(ib + cq) * D + 32 * quad, D, 16, lane);
         }
         tc::fence_async_smem();
         tc::fence_before_sync();
         __syncthreads();
-        // 5. S^T += R^T F ; O^T += R^T C_q^T
+        // 4. O^T += R^T C_q^T (committed first, so its read-back overlaps the state update);
+        //    S^T += R^T F
         if (tid == 0) {
             tc::fence_after_sync();
             const uint32_t aR = sb + OFF_AR;
-#pragma unroll 1
-            for (int ks = 0; ks < 4; ++ks)
-                tc::mma_bf16(tb, tc::sdesc_k(aR, D, ks), tc::sdesc_k(stg + STG_KG, D, ks), tc::idesc_bf16(128, 128), 1);
             if (MODE & 1) {
 #pragma unroll 1
                 for (int ks = 0; ks < 4; ++ks)
                     tc::mma_bf16(tb + 192, tc::sdesc_k(aR, D, ks), tc::sdesc_k(stg + STG_AQ, BT, ks), tc::idesc_bf16(128, 64), 1);
+                tc::mma_commit(&bar[2]);
             }
+#pragma unroll 1
+            for (int ks = 0; ks < 4; ++ks)
+                tc::mma_bf16(tb, tc::sdesc_k(aR, D, ks), tc::sdesc_k(stg + STG_KG, D, ks), tc::idesc_bf16(128, 128), 1);
             tc::mma_commit(&bar[1]);
+        }
+        // 5. output rows of this value column
+        if (MODE & 1) {
+            ok = wait_all(&bar[2], ph2, t.err);
+            ph2 ^= 1;
+            if (!ok) break;
+            tc::fence_after_sync();
+#pragma unroll 1
+            for (int cq = 0; cq < 32; cq += 16) {
+                const int r0 = ib + cq;
+                if (r0 >= len) break;
+                float a[16];
+                tc::tmem_ld16(tl + 192 + r0, a);
+                tc::tmem_wait_ld();
+                tc::warp_store_t16(tst, a, o + ((size_t)(tok0 + r0) * H + h) * D + 32 * quad, (size_t)H * D,
+                                   len - r0, lane);
+            }
+            tc::fence_before_sync();
         }
         ok = wait_all(&bar[1], ph1, t.err);
         ph1 ^= 1;
         if (!ok) break;
         tc::fence_after_sync();
-        // 6. output rows of this value column
-        if (MODE & 1) {
-#pragma unroll 1
-            for (int cb = 0; cb < BT; cb += 16) {
-                if (cb >= len) break;
-                float a[16];
-                tc::tmem_ld16(tl + 192 + cb, a);
-                tc::tmem_wait_ld();
-                tc::warp_store_t16(tst, a, o + ((size_t)(tok0 + cb) * H + h) * D + 32 * warp, (size_t)H * D,
-                                   len - cb, lane);
-            }
-        }
-        tc::fence_before_sync();
-        __syncthreads();
     }
     if (ok && ht) {
         tc::fence_after_sync();
 #pragma unroll 1
-        for (int cb = 0; cb < D; cb += 16) {
+        for (int cb = kb; cb < kb + 64; cb += 16) {
             float a[16];
             tc::tmem_ld16(tl + cb, a);
             tc::tmem_wait_ld();
