@@ -265,7 +265,7 @@ __global__ void __launch_bounds__(ST, 1)
 }
 
 // ================================================== k_bwd_consumer_tc
-constexpr int CT = 256;
+constexpr int CT = 512;   // 16 warps: four warps share each TMEM lane quarter and split columns
 constexpr int LG = D + 1;
 // region X (128 KB): phase A operands, then phase B operands, then final tiles
 constexpr int X_OP = 0;          // [dO ; P]   bf16 [128][128]   32 KB
@@ -276,13 +276,13 @@ constexpr int X_EQ = 0;          // [E_a^T | Q_a^T] tf32 [128][128] 64 KB
 constexpr int X_KZ = 65536;      // (K zeta)^T tf32 [128][64]    32 KB
 constexpr int X_DH = 98304;      // [D ; H_q]^T tf32 [64][128]   32 KB
 constexpr int X_BYTES = 131072;
-constexpr int C_G = X_BYTES;                      // G2 fp32 [64][129]
-constexpr int C_K = C_G + 4 * BT * LG;            // k bf16 [64][128]
+constexpr int C_A = X_BYTES;                      // G2, then alpha = 2^(G2 - c), fp32 [64][129]
+constexpr int C_K = C_A + 4 * BT * LG;            // k bf16 [64][128]
 constexpr int C_Q = C_K + 2 * BT * D;             // q bf16 [64][128]
-constexpr int C_MISC = C_Q + 2 * BT * D;          // small arrays
-constexpr int M_BETA = 0, M_C = 64, M_LAMB = 192, M_DBW = 320, M_ROWA = 384, M_ROWB = 448,
-              M_ENDA = 512, M_ENDB = 640, M_ROW = 768;   // float offsets
-constexpr int C_BAR = C_MISC + 4 * 832;
+constexpr int C_MISC = C_Q + 2 * BT * D;          // small arrays (floats)
+constexpr int M_BETA = 0, M_C2 = 64, M_AL = 192, M_LAMB = 320, M_DBW = 448, M_ROWP = 512,
+              M_ENDP = 768, M_ROW = 1280, M_END = 1344;
+constexpr int C_BAR = C_MISC + 4 * M_END;
 constexpr int CONS_SMEM = C_BAR + 64 + 1024;
 
 __device__ __forceinline__ float bfx(const bf16* p) { return __bfloat162float(*p); }
@@ -297,24 +297,24 @@ __global__ void __launch_bounds__(CT, 1)
     extern __shared__ unsigned char smem_raw[];
     unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                            ~static_cast<uintptr_t>(1023));
-    float* sG = reinterpret_cast<float*>(base + C_G);
+    float* sA = reinterpret_cast<float*>(base + C_A);
     bf16* sK = reinterpret_cast<bf16*>(base + C_K);
     bf16* sQ = reinterpret_cast<bf16*>(base + C_Q);
     float* sm = reinterpret_cast<float*>(base + C_MISC);
     float* sBeta = sm + M_BETA;
-    float* sC = sm + M_C;
-    float* sLamb = sm + M_LAMB;
-    float* sDbw = sm + M_DBW;
-    float* sRowA = sm + M_ROWA;
-    float* sRowB = sm + M_ROWB;
-    float* sEndA = sm + M_ENDA;
-    float* sEndB = sm + M_ENDB;
-    float* sRow = sm + M_ROW;
+    float* sC2 = sm + M_C2;       // 2^c per feature
+    float* sAL = sm + M_AL;       // 2^(G2_last - c) per feature
+    float* sLamb = sm + M_LAMB;   // rowsum(S .* S+bar) per key
+    float* sDbw = sm + M_DBW;     // <v_i, P_i>
+    float* sRowP = sm + M_ROWP;   // [4][64] partial <k_i, gamma E_bar_i>
+    float* sEndP = sm + M_ENDP;   // [4][128] partial sum_j F_j . F_bar_j
+    float* sRow = sm + M_ROW;     // [64] scalar-gate row sums
     uint64_t* bar = reinterpret_cast<uint64_t*>(base + C_BAR);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 1);
     const uint32_t sb = tc::smem_u32(base);
 
     const int c = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quad = warp & 3, grp = warp >> 2;
     const int n = t.chunk_len[c];
     if (n <= 0) return;
     const int H = s.H;
@@ -332,9 +332,8 @@ __global__ void __launch_bounds__(CT, 1)
         tc::tmem_alloc(tslot, 512);
         tc::tmem_relinquish();
     }
-    // phase A operands by cp.async: [dO ; P], R, S, S+bar
+    // phase A operands by cp.async: [dO ; P] (one 128-row tile), R, S, S+bar
     {
-        // one 128-row tile: rows 0..63 = dO (token rows, zero past the chunk), rows 64..127 = P
         const bf16* dO0 = dout + ((size_t)tok0 * H + h) * D;
         const bf16* P0 = b.P + ch * BT * D;
         for (int idx = tid; idx < 2 * BT * 16; idx += CT) {
@@ -350,49 +349,48 @@ __global__ void __launch_bounds__(CT, 1)
         tc::cp_async_commit();
     }
     // raw inputs: k, q (bf16 rows), g (log2 units), beta
-    for (int idx = tid; idx < BT * 16; idx += CT) {
-        const int r = idx >> 4, cc = idx & 15;
-        uint4 kv = make_uint4(0, 0, 0, 0), qv = make_uint4(0, 0, 0, 0);
-        if (r < n) {
-            const size_t off = ((size_t)(tok0 + r) * H + h) * D + cc * 8;
-            kv = *reinterpret_cast<const uint4*>(k + off);
-            qv = *reinterpret_cast<const uint4*>(q + off);
+    {
+        constexpr int NU = BT * D / 8 / CT, NG = BT * D / 4 / CT;
+        uint4 kr4[NU], qr4[NU];
+#pragma unroll
+        for (int u = 0; u < NU; ++u) {
+            const int ci = tid + CT * u, r = ci >> 4, c8 = (ci & 15) * 8;
+            kr4[u] = qr4[u] = make_uint4(0, 0, 0, 0);
+            if (r < n) {
+                const size_t off = ((size_t)(tok0 + r) * H + h) * D + c8;
+                kr4[u] = __ldg(reinterpret_cast<const uint4*>(k + off));
+                qr4[u] = __ldg(reinterpret_cast<const uint4*>(q + off));
+            }
         }
-        *reinterpret_cast<uint4*>(sK + r * D + cc * 8) = kv;
-        *reinterpret_cast<uint4*>(sQ + r * D + cc * 8) = qv;
-    }
-    for (int idx = tid; idx < BT * D; idx += CT) {
-        const int r = idx >> 7, col = idx & (D - 1);
-        float gv = 0.f;
-        if (r < n) {
-            if (GATE == 2) gv = g[((size_t)(tok0 + r) * H + h) * D + col] * LOG2E;
-            if (GATE == 1) gv = g[(size_t)(tok0 + r) * H + h] * LOG2E;
+        float4 gr4[NG];
+#pragma unroll
+        for (int u = 0; u < NG; ++u) {
+            const int ci = tid + CT * u, r = ci >> 5, c4 = (ci & 31) * 4;
+            gr4[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (r < n) {
+                if (GATE == 2) gr4[u] = __ldg(reinterpret_cast<const float4*>(g + ((size_t)(tok0 + r) * H + h) * D + c4));
+                if (GATE == 1) {
+                    const float x = __ldg(g + (size_t)(tok0 + r) * H + h);
+                    gr4[u] = make_float4(x, x, x, x);
+                }
+            }
         }
-        sG[r * LG + col] = gv;
+#pragma unroll
+        for (int u = 0; u < NU; ++u) {
+            const int ci = tid + CT * u, r = ci >> 4, c8 = (ci & 15) * 8;
+            *reinterpret_cast<uint4*>(sK + r * D + c8) = kr4[u];
+            *reinterpret_cast<uint4*>(sQ + r * D + c8) = qr4[u];
+        }
+#pragma unroll
+        for (int u = 0; u < NG; ++u) {
+            const int ci = tid + CT * u, r = ci >> 5, c4 = (ci & 31) * 4;
+            sA[r * LG + c4] = gr4[u].x * LOG2E;
+            sA[r * LG + c4 + 1] = gr4[u].y * LOG2E;
+            sA[r * LG + c4 + 2] = gr4[u].z * LOG2E;
+            sA[r * LG + c4 + 3] = gr4[u].w * LOG2E;
+        }
     }
     if (tid < BT) sBeta[tid] = (tid < n) ? bfx(beta + (size_t)(tok0 + tid) * H + h) : 0.f;
-    // dv = beta P and <v_i, P_i>: warp w handles rows w, w+8, ..
-    for (int r = warp; r < BT; r += CT / 32) {
-        float acc = 0.f;
-        if (r < n) {
-            const size_t tok = (size_t)(tok0 + r) * H + h;
-            const float bt = bfx(beta + tok);
-            const bf16* Pr = b.P + ch * BT * D + (size_t)r * D + lane * 4;
-            const bf16* vr = v + tok * D + lane * 4;
-            uint32_t out[2];
-#pragma unroll
-            for (int e = 0; e < 4; e += 2) {
-                const float p0 = bfx(Pr + e), p1 = bfx(Pr + e + 1);
-                acc = fmaf(bfx(vr + e), p0, acc);
-                acc = fmaf(bfx(vr + e + 1), p1, acc);
-                out[e / 2] = tc::pack_bf16(bt * p0, bt * p1);
-            }
-            *reinterpret_cast<uint2*>(dv + tok * D + lane * 4) = make_uint2(out[0], out[1]);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        if (lane == 0) sDbw[r] = acc;
-    }
     tc::cp_async_wait_all();
     tc::fence_async_smem();
     tc::fence_before_sync();
@@ -414,27 +412,52 @@ __global__ void __launch_bounds__(CT, 1)
             tc::mma_bf16(tb + 192, tc::sdesc_k(sb + X_SB, D, ks), tc::sdesc_k(sb + X_R, BT, ks), i64, ks > 0);
         tc::mma_commit(bar);
     }
-    // while the MMAs run: cumsum, centers, rowsum(S .* S+bar) from HBM
-    if (tid < D) {
+    // while the MMAs run: cumsum (4 segments of 16 rows per feature), anchors, alpha tile;
+    // rowsum(S .* S+bar) and <v_i, P_i>, dv = beta P from the staged tiles
+    {
+        const int col = tid >> 2, seg = tid & 3;
+        float x[16];
         float acc = 0.f;
-        for (int r = 0; r < BT; ++r) {
-            acc += sG[r * LG + tid];
-            sG[r * LG + tid] = acc;
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            acc += sA[(16 * seg + r) * LG + col];
+            x[r] = acc;
         }
-        float hi = sG[tid], lo = sG[tid];
-        for (int r = 1; r < n; ++r) {
-            hi = fmaxf(hi, sG[r * LG + tid]);
-            lo = fminf(lo, sG[r * LG + tid]);
+        float pre = __shfl_up_sync(0xffffffffu, acc, 1, 4);
+        if (seg < 1) pre = 0.f;
+        float t2 = __shfl_up_sync(0xffffffffu, acc + pre, 2, 4);
+        if (seg < 2) t2 = 0.f;
+        const float off = pre + t2;
+        float hi = -INFINITY, lo = INFINITY;
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            x[r] += off;
+            if (16 * seg + r < n) {
+                hi = fmaxf(hi, x[r]);
+                lo = fminf(lo, x[r]);
+            }
         }
-        sC[tid] = (GATE == 2) ? 0.5f * (hi + lo) : 0.f;
-    } else {
-        const int kr = tid - D;
-        const uint4* hs = reinterpret_cast<const uint4*>(f.HS + ch * D * D + (size_t)kr * D);
-        const uint4* sbp = reinterpret_cast<const uint4*>(b.SBP + ch * D * D + (size_t)kr * D);
+        hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, 1));
+        hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, 2));
+        lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, 1));
+        lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, 2));
+        const float cc = (GATE == 0) ? 0.f : 0.5f * (hi + lo);
+        const float glast = __shfl_sync(0xffffffffu, x[15], (lane & ~3) | 3);
+#pragma unroll
+        for (int r = 0; r < 16; ++r) sA[(16 * seg + r) * LG + col] = exp2f(x[r] - cc);
+        if (seg == 0) {
+            sC2[col] = exp2f(cc);
+            sAL[col] = exp2f(glast - cc);
+        }
+    }
+    if (tid < D) {
+        const int kr = tid;
         float acc = 0.f;
 #pragma unroll 4
         for (int cc = 0; cc < 16; ++cc) {
-            const uint4 a = hs[cc], bb = sbp[cc];
+            const uint32_t o = tc::sw128_off(D, kr, cc * 16);
+            const uint4 a = *reinterpret_cast<const uint4*>(base + X_S + o);
+            const uint4 bb = *reinterpret_cast<const uint4*>(base + X_SB + o);
             const bf16* pa = reinterpret_cast<const bf16*>(&a);
             const bf16* pb = reinterpret_cast<const bf16*>(&bb);
 #pragma unroll
@@ -442,35 +465,58 @@ __global__ void __launch_bounds__(CT, 1)
         }
         sLamb[kr] = acc;
     }
+    for (int idx = tid; idx < BT * 16; idx += CT) {   // 16 threads per row, 8 values each
+        const int r = idx >> 4, cc = idx & 15;
+        float acc = 0.f;
+        if (r < n) {
+            const size_t tok = (size_t)(tok0 + r) * H + h;
+            const float bt = bfx(beta + tok);
+            const uint4 pp = *reinterpret_cast<const uint4*>(base + X_OP + tc::sw128_off(2 * BT, BT + r, cc * 16));
+            const uint4 vv = __ldg(reinterpret_cast<const uint4*>(v + tok * D + cc * 8));
+            const bf16* pp2 = reinterpret_cast<const bf16*>(&pp);
+            const bf16* vv2 = reinterpret_cast<const bf16*>(&vv);
+            uint32_t out[4];
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+                const float p0 = __bfloat162float(pp2[e]), p1 = __bfloat162float(pp2[e + 1]);
+                acc = fmaf(__bfloat162float(vv2[e]), p0, acc);
+                acc = fmaf(__bfloat162float(vv2[e + 1]), p1, acc);
+                out[e / 2] = tc::pack_bf16(bt * p0, bt * p1);
+            }
+            *reinterpret_cast<uint4*>(dv + tok * D + cc * 8) = make_uint4(out[0], out[1], out[2], out[3]);
+        }
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o, 16);
+        if (cc == 0) sDbw[r] = acc;
+    }
     bool ok = wait_all(bar, 0, t.err);
     if (ok) {
         tc::fence_after_sync();
-        // ---- epilogue A: mask [H_q ; -D] into [H_q ; D] (scalar gate: fold the pairwise decay),
-        // keep it in TMEM as the A operand of [T_q ; T_e], and write its transpose as B of T_y^T
+        // ---- epilogue A: mask [H_q ; -D] into [H_q ; D] (scalar gate: fold the pairwise decay
+        // alpha_i / alpha_j), keep it in TMEM as the A operand of [T_q ; T_e], and write its
+        // transpose as the B operand of T_y^T
         {
-            const int row = 32 * (warp & 3) + lane, cb0 = (warp >> 2) * 32;
-            const uint32_t ta = tc::taddr(tb, 32 * (warp & 3), cb0);
-            float a[32];
-            tc::tmem_ld16(ta, *reinterpret_cast<float(*)[16]>(a));
-            tc::tmem_ld16(ta + 16, *reinterpret_cast<float(*)[16]>(a + 16));
+            const int row = 32 * quad + lane, cb0 = grp * 16;
+            const uint32_t ta = tc::taddr(tb, 32 * quad, cb0);
+            float a[16];
+            tc::tmem_ld16(ta, a);
             tc::tmem_wait_ld();
             const bool isH = row < BT;
             const int i = isH ? row : row - BT;
-            const float gi = sG[i * LG];
+            const float ai = sA[i * LG];
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
+            for (int jj = 0; jj < 16; ++jj) {
                 const int j = cb0 + jj;
                 float x = (i < n && (isH ? j <= i : j < i)) ? (isH ? a[jj] : -a[jj]) : 0.f;
-                if (GATE == 1) x *= exp2f(fminf(gi - sG[j * LG], 0.f));
+                if (GATE == 1) x *= fminf(ai * __frcp_rn(sA[j * LG]), 1.f);
                 a[jj] = x;
                 const int kidx = isH ? BT + i : i;   // K order of T_y^T: D rows first, then H_q rows
                 *reinterpret_cast<float*>(base + X_DH + tc::sw128_off(BT, j, kidx * 4)) = x;
             }
-            tc::tmem_st16(ta, *reinterpret_cast<float(*)[16]>(a));
-            tc::tmem_st16(ta + 16, *reinterpret_cast<float(*)[16]>(a + 16));
+            tc::tmem_st16(ta, a);
             tc::tmem_wait_st();
         }
-        // (K zeta)^T: rows = key k, K = token j
+        // (K zeta)^T: rows = key k, K = token j (zeta = 1/alpha; unit without a per-channel gate)
         for (int idx = tid; idx < D * 16; idx += CT) {
             const int kr = idx & (D - 1), cc = idx >> 7;
             float4 val;
@@ -479,7 +525,7 @@ __global__ void __launch_bounds__(CT, 1)
             for (int e = 0; e < 4; ++e) {
                 const int j = 4 * cc + e;
                 const float kv = __bfloat162float(sK[j * D + kr]);
-                pv[e] = (GATE == 2) ? kv * exp2f(sC[kr] - sG[j * LG + kr]) : kv;
+                pv[e] = (GATE == 2) ? kv * __frcp_rn(sA[j * LG + kr]) : kv;
             }
             *reinterpret_cast<float4*>(base + X_KZ + tc::sw128_off(D, kr, cc * 16)) = val;
         }
@@ -492,7 +538,7 @@ __global__ void __launch_bounds__(CT, 1)
             for (int e = 0; e < 4; ++e) {
                 const int kk = 4 * cc + e;
                 const int j = kk & (BT - 1);
-                const float al = (GATE == 2) ? exp2f(sG[j * LG + kr] - sC[kr]) : 1.f;
+                const float al = (GATE == 2) ? sA[j * LG + kr] : 1.f;
                 pv[e] = (kk < BT) ? sBeta[j] * __bfloat162float(sK[j * D + kr]) * al
                                   : scale * __bfloat162float(sQ[j * D + kr]) * al;
             }
@@ -519,117 +565,128 @@ __global__ void __launch_bounds__(CT, 1)
         float* sDK = reinterpret_cast<float*>(base);              // [64][129] beta*gamma*E_bar + Y_bar/gamma
         float* sGQ = sDK + BT * LG;                               // [64][129] G_bar (query and key-side parts)
         float* sGE = sGQ + BT * LG;                               // [64][129] G_bar (erase part)
-        // ---- F1: rows of [T_q ; T_e] and [dO S^T ; P S^T]
+        // ---- F1: rows of [T_q ; T_e] and [dO S^T ; P S^T]; four warps per lane quarter, 32 columns each
         {
-            const int row = 32 * (warp & 3) + lane, cb0 = (warp >> 2) * 64;
+            const int row = 32 * quad + lane, cb0 = grp * 32;
             const bool isQ = row < BT;
             const int i = isQ ? row : row - BT;
             const float bt = sBeta[i];
             float part = 0.f;
-            uint32_t packed[32];
+            uint32_t packed[16];
 #pragma unroll
-            for (int cb = 0; cb < 64; cb += 16) {
+            for (int cb = 0; cb < 32; cb += 16) {
                 float tq[16], tp[16];
-                tc::tmem_ld16(tc::taddr(tb + 256, 32 * (warp & 3), cb0 + cb), tq);
-                tc::tmem_ld16(tc::taddr(tb + 64, 32 * (warp & 3), cb0 + cb), tp);
+                tc::tmem_ld16(tc::taddr(tb + 256, 32 * quad, cb0 + cb), tq);
+                tc::tmem_ld16(tc::taddr(tb + 64, 32 * quad, cb0 + cb), tp);
                 tc::tmem_wait_ld();
 #pragma unroll
                 for (int jj = 0; jj < 16; ++jj) {
                     const int kr = cb0 + cb + jj;
-                    const float gk = sG[i * LG + kr];
-                    const float al = (GATE == 2) ? exp2f(gk - sC[kr]) : 1.f;
-                    const float gam = exp2f(gk);
+                    const float al = sA[i * LG + kr];
+                    const float fac = (GATE == 2) ? al : 1.f;      // alpha (unit: folded / no gate)
+                    const float gam = al * sC2[kr];                 // gamma = 2^G2
                     if (isQ) {
-                        const float Qt = al * tq[jj] + gam * tp[jj];               // gamma * Q_g_bar
+                        const float Qt = fac * tq[jj] + gam * tp[jj];               // gamma * Q_g_bar
                         sGQ[i * LG + kr] = scale * __bfloat162float(sQ[i * D + kr]) * Qt;
-                        if (jj & 1) packed[(cb + jj) / 2] = tc::pack_bf16(tq[jj - 1], scale * Qt);
-                        else tq[jj] = scale * Qt;  // stash for the pair
+                        tq[jj] = scale * Qt;
                     } else {
-                        const float Et = al * tq[jj] - gam * tp[jj];               // gamma * E_bar
+                        const float Et = fac * tq[jj] - gam * tp[jj];               // gamma * E_bar
                         const float kv = __bfloat162float(sK[i * D + kr]);
                         sDK[i * LG + kr] = bt * Et;
                         sGE[i * LG + kr] = bt * kv * Et;
                         part = fmaf(kv, Et, part);
                     }
                 }
+                if (isQ) {
+#pragma unroll
+                    for (int jj = 0; jj < 8; ++jj) packed[cb / 2 + jj] = tc::pack_bf16(tq[2 * jj], tq[2 * jj + 1]);
+                }
             }
             if (isQ) {
                 if (i < n) {
                     uint4* dst = reinterpret_cast<uint4*>(dq + ((size_t)(tok0 + i) * H + h) * D + cb0);
 #pragma unroll
-                    for (int qq = 0; qq < 8; ++qq)
+                    for (int qq = 0; qq < 4; ++qq)
                         dst[qq] = make_uint4(packed[4 * qq], packed[4 * qq + 1], packed[4 * qq + 2], packed[4 * qq + 3]);
                 }
             } else {
-                if (warp < 4) sRowA[i] = part;
-                else sRowB[i] = part;
+                sRowP[grp * BT + i] = part;
             }
         }
         __syncthreads();
-        // ---- F2: T_y^T and F_bar^T rows = key k, columns = token j
+        // ---- F2: T_y^T and F_bar^T rows = key k, columns = token j; 16 columns per warp
         {
-            const int kr = 32 * (warp & 3) + lane, cb0 = (warp >> 2) * 32;
-            const float glk = sG[(n - 1) * LG + kr];
+            const int kr = 32 * quad + lane, cb0 = grp * 16;
+            const float al_last = sAL[kr];
             float endp = 0.f;
-#pragma unroll 1
-            for (int cb = 0; cb < 32; cb += 16) {
-                float ty[16], fb[16];
-                tc::tmem_ld16(tc::taddr(tb + 384, 32 * (warp & 3), cb0 + cb), ty);
-                tc::tmem_ld16(tc::taddr(tb + 192, 32 * (warp & 3), cb0 + cb), fb);
-                tc::tmem_wait_ld();
+            float ty[16], fb[16];
+            tc::tmem_ld16(tc::taddr(tb + 384, 32 * quad, cb0), ty);
+            tc::tmem_ld16(tc::taddr(tb + 192, 32 * quad, cb0), fb);
+            tc::tmem_wait_ld();
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) {
-                    const int j = cb0 + cb + jj;
-                    const float gj = sG[j * LG + kr];
-                    const float ze = (GATE == 2) ? exp2f(sC[kr] - gj) : 1.f;
-                    const float dec = exp2f(glk - gj);                  // lambda / gamma_j
-                    const float Yt = ze * ty[jj] + fb[jj] * dec;        // Y_bar / gamma
-                    const float kv = __bfloat162float(sK[j * D + kr]);
-                    sDK[j * LG + kr] += Yt;
-                    sGQ[j * LG + kr] -= kv * Yt;
-                    if (j < n) endp = fmaf(kv * dec, fb[jj], endp);      // F_j . F_bar_j
-                }
+            for (int jj = 0; jj < 16; ++jj) {
+                const int j = cb0 + jj;
+                const float rinv = __frcp_rn(sA[j * LG + kr]);
+                const float ze = (GATE == 2) ? rinv : 1.f;
+                const float dec = al_last * rinv;                   // lambda / gamma_j
+                const float Yt = ze * ty[jj] + fb[jj] * dec;        // Y_bar / gamma
+                const float kv = __bfloat162float(sK[j * D + kr]);
+                sDK[j * LG + kr] += Yt;
+                sGQ[j * LG + kr] -= kv * Yt;
+                if (j < n) endp = fmaf(kv * dec, fb[jj], endp);      // F_j . F_bar_j
             }
-            if (warp < 4) sEndA[kr] = endp;
-            else sEndB[kr] = endp;
+            sEndP[grp * D + kr] = endp;
         }
         __syncthreads();
         // ---- F3: dk, dbeta, dg
         for (int idx = tid; idx < BT * D / 8; idx += CT) {
             const int r = idx >> 4, cc = idx & 15;
             if (r < n) {
-                uint4 pk;
-                uint32_t* pw = reinterpret_cast<uint32_t*>(&pk);
+                uint32_t pw[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
                     pw[e] = tc::pack_bf16(sDK[r * LG + cc * 8 + 2 * e], sDK[r * LG + cc * 8 + 2 * e + 1]);
-                *reinterpret_cast<uint4*>(dk + ((size_t)(tok0 + r) * H + h) * D + cc * 8) = pk;
+                *reinterpret_cast<uint4*>(dk + ((size_t)(tok0 + r) * H + h) * D + cc * 8) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
             }
         }
         if (tid < BT && tid < n)
-            dbeta[(size_t)(tok0 + tid) * H + h] = __float2bfloat16_rn(sRowA[tid] + sRowB[tid] + sDbw[tid]);
+            dbeta[(size_t)(tok0 + tid) * H + h] = __float2bfloat16_rn(sRowP[tid] + sRowP[BT + tid] + sRowP[2 * BT + tid] +
+                                                                      sRowP[3 * BT + tid] + sDbw[tid]);
         if (GATE != 0) {
             if (tid < D) {
-                const float glk = sG[(n - 1) * LG + tid];
-                const float endp = exp2f(glk) * sLamb[tid] + sEndA[tid] + sEndB[tid];
+                const float lam = sAL[tid] * sC2[tid];   // 2^G2_last
+                const float endp = lam * sLamb[tid] + sEndP[tid] + sEndP[D + tid] + sEndP[2 * D + tid] + sEndP[3 * D + tid];
                 sGQ[(n - 1) * LG + tid] += endp;
             }
             __syncthreads();
             if (GATE == 2) {
-                if (tid < D) {
-                    float acc = 0.f;
-                    for (int r = n - 1; r >= 0; --r) {
-                        acc += sGQ[r * LG + tid] + sGE[r * LG + tid];
-                        dg[((size_t)(tok0 + r) * H + h) * D + tid] = acc;
-                    }
+                // reverse in-chunk cumsum by 4 segments of 16 rows per feature
+                const int col = tid >> 2, seg = tid & 3;
+                float x[16];
+                float acc = 0.f;
+#pragma unroll
+                for (int r = 15; r >= 0; --r) {
+                    const int row = 16 * seg + r;
+                    acc += (row < n) ? sGQ[row * LG + col] + sGE[row * LG + col] : 0.f;
+                    x[r] = acc;
+                }
+                float nxt = __shfl_down_sync(0xffffffffu, acc, 1, 4);
+                if (seg > 2) nxt = 0.f;
+                float t2 = __shfl_down_sync(0xffffffffu, acc + nxt, 2, 4);
+                if (seg > 1) t2 = 0.f;
+                const float off = nxt + t2;  // sum of the later segments
+#pragma unroll
+                for (int r = 0; r < 16; ++r) {
+                    const int row = 16 * seg + r;
+                    if (row < n) dg[((size_t)(tok0 + row) * H + h) * D + col] = x[r] + off;
                 }
             } else {
                 for (int r = warp; r < BT; r += CT / 32) {
-                    float x = 0.f;
-                    for (int col = lane; col < D; col += 32) x += sGQ[r * LG + col] + sGE[r * LG + col];
+                    float xs = 0.f;
+                    for (int col = lane; col < D; col += 32) xs += sGQ[r * LG + col] + sGE[r * LG + col];
 #pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-                    if (lane == 0) sRow[r] = x;
+                    for (int o = 16; o > 0; o >>= 1) xs += __shfl_xor_sync(0xffffffffu, xs, o);
+                    if (lane == 0) sRow[r] = xs;
                 }
                 __syncthreads();
                 if (tid == 0) {

@@ -41,7 +41,7 @@ __device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, int32_t
 }
 
 // =========================================================== k_prep_tc
-constexpr int PT = 256;
+constexpr int PT = 512;
 constexpr int LG = D + 1;  // padded row stride of fp32 [64 x 128] tiles
 constexpr int LA = BT + 1;
 constexpr int LW = D + 8;   // row stride (bf16) of the staged W tile
@@ -54,7 +54,7 @@ constexpr int LQ = BT + 8;  // row stride (bf16) of the staged C_q tile
 //     A_ij = -A_ii * sum_{m=j}^{i-1} L_im A_mj,
 // the 4 x 4 block merge of the GatedDeltaNet-2 spec transcription (section 2.4).
 __device__ __forceinline__ void blocked_inverse(const float* sL, float* sA, float* sT, int tid) {
-    {
+    if (tid < 4 * BT) {  // whole warps: 64 threads per diagonal block, 4 lanes per column
         const int blk = tid >> 6, col = (tid >> 2) & 15, part = tid & 3;
         const int o = blk * BC;
         for (int r = part; r < BT; r += 4) sA[r * LA + o + col] = 0.f;
@@ -107,15 +107,16 @@ __global__ void __launch_bounds__(PT, 1)
                                                            ~static_cast<uintptr_t>(1023));
     unsigned char* R1 = base;             // 64 KB operand region (1024-aligned)
     unsigned char* R2 = R1 + 65536;       // 32 KB operand region
-    float* sG = reinterpret_cast<float*>(R2 + 32768);  // [64][129] cumulative log2-decay
-    bf16* sK = reinterpret_cast<bf16*>(sG + BT * LG);  // [64][128] keys
+    float* sA = reinterpret_cast<float*>(R2 + 32768);  // [64][129] G2, then alpha = 2^(G2 - c)
+    bf16* sK = reinterpret_cast<bf16*>(sA + BT * LG);  // [64][128] keys
     bf16* sQ = sK + BT * D;                             // [64][128] queries
     float* sAkk = reinterpret_cast<float*>(sQ + BT * D);  // [64][65]
     float* sAi = sAkk + BT * LA;          // [64][65]
     float* sT = sAi + BT * LA;            // [3][16][17] merge temporaries
     float* sBeta = sT + 3 * BC * (BC + 1);  // [64]
-    float* sC = sBeta + BT;               // [128] anchor per feature
-    uint64_t* bar = reinterpret_cast<uint64_t*>(sC + D);
+    float* sC2 = sBeta + BT;              // [128] 2^c (c = midpoint anchor of the feature)
+    float* sAL = sC2 + D;                 // [128] 2^(G2_last - c)
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sAL + D);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 1);
 
     const int c = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -127,9 +128,11 @@ __global__ void __launch_bounds__(PT, 1)
     const float scale = s.scale;
 
     // ---- batched vector loads: k, q, v (bf16, 8 per 16 B), g (fp32, 4 per 16 B)
-    uint4 kr4[4], qr4[4], vr4[4];
+    constexpr int NU = BT * D / 8 / PT;   // 16-byte bf16 chunks per thread
+    constexpr int NG = BT * D / 4 / PT;   // 16-byte fp32 chunks per thread
+    uint4 kr4[NU], qr4[NU], vr4[NU];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < NU; ++u) {
         const int ci = tid + PT * u, r = ci >> 4, c8 = (ci & 15) * 8;
         kr4[u] = qr4[u] = vr4[u] = make_uint4(0, 0, 0, 0);
         if (r < n) {
@@ -139,9 +142,9 @@ __global__ void __launch_bounds__(PT, 1)
             vr4[u] = __ldg(reinterpret_cast<const uint4*>(v + off));
         }
     }
-    float4 gr4[8];
+    float4 gr4[NG];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
+    for (int u = 0; u < NG; ++u) {
         const int ci = tid + PT * u, r = ci >> 5, c4 = (ci & 31) * 4;
         gr4[u] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (r < n) {
@@ -154,18 +157,18 @@ __global__ void __launch_bounds__(PT, 1)
     }
     if (tid < BT) sBeta[tid] = (tid < n) ? bfx(beta + (size_t)(tok0 + tid) * H + h) : 0.f;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < NU; ++u) {
         const int ci = tid + PT * u, r = ci >> 4, c8 = (ci & 15) * 8;
         *reinterpret_cast<uint4*>(sK + r * D + c8) = kr4[u];
         *reinterpret_cast<uint4*>(sQ + r * D + c8) = qr4[u];
     }
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
+    for (int u = 0; u < NG; ++u) {
         const int ci = tid + PT * u, r = ci >> 5, c4 = (ci & 31) * 4;
-        sG[r * LG + c4] = gr4[u].x * LOG2E;
-        sG[r * LG + c4 + 1] = gr4[u].y * LOG2E;
-        sG[r * LG + c4 + 2] = gr4[u].z * LOG2E;
-        sG[r * LG + c4 + 3] = gr4[u].w * LOG2E;
+        sA[r * LG + c4] = gr4[u].x * LOG2E;
+        sA[r * LG + c4 + 1] = gr4[u].y * LOG2E;
+        sA[r * LG + c4 + 2] = gr4[u].z * LOG2E;
+        sA[r * LG + c4 + 3] = gr4[u].w * LOG2E;
     }
     if (tid == 0) {
         tc::mbar_init(bar, 1);
@@ -180,50 +183,69 @@ __global__ void __launch_bounds__(PT, 1)
     tc::fence_after_sync();
     const uint32_t tb = *tslot;
 
-    // a1: cumsum, range, midpoint anchor
+    // a1: cumsum by 4 segments of 16 rows per feature (lanes 4c..4c+3), range, midpoint anchor;
+    // then alpha = 2^(G2 - c) replaces G2 (one exp2 per element; every other decay factor of
+    // this chunk is alpha times a per-feature constant or its reciprocal)
     int wide_col = 0;
-    if (tid < D) {
+    if (tid < 4 * D) {
+        const int col = tid >> 2, seg = tid & 3;
+        float x[16];
         float acc = 0.f;
-        for (int r = 0; r < BT; ++r) {
-            acc += sG[r * LG + tid];
-            sG[r * LG + tid] = acc;
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            acc += sA[(16 * seg + r) * LG + col];
+            x[r] = acc;
         }
-        float hi = sG[tid], lo = sG[tid];
-        for (int r = 1; r < n; ++r) {
-            hi = fmaxf(hi, sG[r * LG + tid]);
-            lo = fminf(lo, sG[r * LG + tid]);
+        float pre = __shfl_up_sync(0xffffffffu, acc, 1, 4);
+        if (seg < 1) pre = 0.f;
+        float t2 = __shfl_up_sync(0xffffffffu, acc + pre, 2, 4);
+        if (seg < 2) t2 = 0.f;
+        const float off = pre + t2;  // exclusive prefix of the segment totals
+        float hi = -INFINITY, lo = INFINITY;
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            x[r] += off;
+            if (16 * seg + r < n) {
+                hi = fmaxf(hi, x[r]);
+                lo = fminf(lo, x[r]);
+            }
         }
-        sC[tid] = 0.5f * (hi + lo);
+        hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, 1));
+        hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, 2));
+        lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, 1));
+        lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, 2));
+        const float cc = 0.5f * (hi + lo);
+        const float glast = __shfl_sync(0xffffffffu, x[15], (lane & ~3) | 3);  // G2 at row 63 = last token
+#pragma unroll
+        for (int r = 0; r < 16; ++r) sA[(16 * seg + r) * LG + col] = exp2f(x[r] - cc);
+        if (seg == 0) {
+            sC2[col] = exp2f(cc);
+            sAL[col] = exp2f(glast - cc);
+            f.GL[ch * D + col] = glast;
+        }
         wide_col = (hi - lo) > PREP_RANGE_LOG2;
     }
     const bool wide = __syncthreads_or(wide_col) != 0;
     if (tid == 0) f.WIDE[ch] = wide ? 1 : 0;
     bool ok = true;
     if (!wide) {
-        // a2 operands (tf32): A rows 0..63 beta_i k_i 2^(G_i-c), rows 64..127 s q_i 2^(G_i-c);
-        // B rows j: k_j 2^(c-G_j)
+        // a2 operands (tf32): A rows 0..63 beta_i k_i alpha_i, rows 64..127 s q_i alpha_i;
+        // B rows j: k_j / alpha_j
         for (int idx = tid; idx < 2 * BT * 32; idx += PT) {
             const int r = idx >> 5, cc = idx & 31, i = r & (BT - 1);
-            float4 val;
-            float* pv = reinterpret_cast<float*>(&val);
             const bf16* src = (r < BT ? sK : sQ) + i * D + 4 * cc;
             const float mul = (r < BT) ? sBeta[i] : scale;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int col = 4 * cc + e;
-                pv[e] = mul * __bfloat162float(src[e]) * exp2f(sG[i * LG + col] - sC[col]);
-            }
+            const float* al = sA + i * LG + 4 * cc;
+            const float4 val = make_float4(mul * __bfloat162float(src[0]) * al[0], mul * __bfloat162float(src[1]) * al[1],
+                                           mul * __bfloat162float(src[2]) * al[2], mul * __bfloat162float(src[3]) * al[3]);
             *reinterpret_cast<float4*>(R1 + tc::sw128_off(2 * BT, r, cc * 16)) = val;
         }
         for (int idx = tid; idx < BT * 32; idx += PT) {
             const int j = idx >> 5, cc = idx & 31;
-            float4 val;
-            float* pv = reinterpret_cast<float*>(&val);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int col = 4 * cc + e;
-                pv[e] = __bfloat162float(sK[j * D + col]) * exp2f(sC[col] - sG[j * LG + col]);
-            }
+            const bf16* src = sK + j * D + 4 * cc;
+            const float* al = sA + j * LG + 4 * cc;
+            const float4 val = make_float4(__bfloat162float(src[0]) * __frcp_rn(al[0]), __bfloat162float(src[1]) * __frcp_rn(al[1]),
+                                           __bfloat162float(src[2]) * __frcp_rn(al[2]), __bfloat162float(src[3]) * __frcp_rn(al[3]));
             *reinterpret_cast<float4*>(R2 + tc::sw128_off(BT, j, cc * 16)) = val;
         }
         tc::fence_async_smem();
@@ -242,25 +264,24 @@ __global__ void __launch_bounds__(PT, 1)
     if (!wide && ok) {
         tc::fence_after_sync();
         bf16* sAq = reinterpret_cast<bf16*>(R2 + 16384);  // staged C_q [64][72] (transposed copy)
-        // read back [Akk ; Aqk]: warps w and w+4 share lanes 32(w%4).., split the 64 columns
+        // read back [Akk ; Aqk]: warps w, w+4, w+8, w+12 share lanes 32(w%4).., split the 64 columns
         {
-            const int row = 32 * (warp & 3) + lane, cb = (warp >> 2) * 32;
-            float a[32];
-            tc::tmem_ld16(tc::taddr(tb, 32 * (warp & 3), cb), *reinterpret_cast<float(*)[16]>(a));
-            tc::tmem_ld16(tc::taddr(tb, 32 * (warp & 3), cb + 16), *reinterpret_cast<float(*)[16]>(a + 16));
+            const int row = 32 * (warp & 3) + lane, cb = (warp >> 2) * 16;
+            float a[16];
+            tc::tmem_ld16(tc::taddr(tb, 32 * (warp & 3), cb), a);
             tc::tmem_wait_ld();
             if (row < BT) {
                 const int i = row;
 #pragma unroll
-                for (int jj = 0; jj < 32; ++jj) {
+                for (int jj = 0; jj < 16; ++jj) {
                     const int j = cb + jj;
                     sAkk[i * LA + j] = (j < i && i < n) ? a[jj] : 0.f;
                 }
             } else {
                 const int i = row - BT;
-                uint32_t pw[16];
+                uint32_t pw[8];
 #pragma unroll
-                for (int jj = 0; jj < 32; jj += 2) {
+                for (int jj = 0; jj < 16; jj += 2) {
                     const int j = cb + jj;
                     const float x0 = (j <= i && i < n) ? a[jj] : 0.f;
                     const float x1 = (j + 1 <= i && i < n) ? a[jj + 1] : 0.f;
@@ -271,29 +292,30 @@ __global__ void __launch_bounds__(PT, 1)
                     }
                 }
                 uint4* dst = reinterpret_cast<uint4*>(f.AQK + ch * BT * BT + (size_t)i * BT + cb);
-#pragma unroll
-                for (int qq = 0; qq < 4; ++qq) dst[qq] = make_uint4(pw[4 * qq], pw[4 * qq + 1], pw[4 * qq + 2], pw[4 * qq + 3]);
+                dst[0] = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+                dst[1] = make_uint4(pw[4], pw[5], pw[6], pw[7]);
             }
         }
         tc::fence_before_sync();
         __syncthreads();
         // a3: A = (I + Akk)^-1
         blocked_inverse(sAkk, sAi, sT, tid);
-        // a4 operands (tf32): R1 <- E^T [128 keys][64 tokens], R1+32K <- Z^T [128 values][64 tokens],
-        // R2 <- A [64 rows i][64 cols j] (B operand of W^T = E^T A^T, K = j)
+        // a4 operands (tf32): R1 <- E^T [128 keys][64 tokens] (beta k 2^G2 = beta k alpha 2^c),
+        // R1+32K <- Z^T [128 values][64 tokens], R2 <- A [64 rows i][64 cols j]
         for (int idx = tid; idx < D * 16; idx += PT) {
             const int kr = idx & (D - 1), cc = idx >> 7;
             float4 val;
             float* pv = reinterpret_cast<float*>(&val);
+            const float c2 = sC2[kr];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int j = 4 * cc + e;
-                pv[e] = sBeta[j] * __bfloat162float(sK[j * D + kr]) * exp2f(sG[j * LG + kr]);
+                pv[e] = sBeta[j] * __bfloat162float(sK[j * D + kr]) * sA[j * LG + kr] * c2;
             }
             *reinterpret_cast<float4*>(R1 + tc::sw128_off(D, kr, cc * 16)) = val;
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < NU; ++u) {
             const int ci = tid + PT * u, j = ci >> 4, c8 = (ci & 15) * 8;
             const bf16* pv = reinterpret_cast<const bf16*>(&vr4[u]);
 #pragma unroll
@@ -302,11 +324,8 @@ __global__ void __launch_bounds__(PT, 1)
         }
         for (int idx = tid; idx < BT * 16; idx += PT) {
             const int i = idx >> 4, cc = idx & 15;
-            float4 val;
-            float* pv = reinterpret_cast<float*>(&val);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) pv[e] = sAi[i * LA + 4 * cc + e];
-            *reinterpret_cast<float4*>(R2 + tc::sw128_off(BT, i, cc * 16)) = val;
+            const float* ai = sAi + i * LA + 4 * cc;
+            *reinterpret_cast<float4*>(R2 + tc::sw128_off(BT, i, cc * 16)) = make_float4(ai[0], ai[1], ai[2], ai[3]);
         }
         tc::fence_async_smem();
         tc::fence_before_sync();
@@ -322,20 +341,20 @@ __global__ void __launch_bounds__(PT, 1)
             tc::mma_commit(bar);
         }
         // element-wise outputs while the MMAs run, as 16-byte stores:
-        // Q_g [i][k] (+ Q_g^T), F^T [k][i] (+ F), A^T [j][i], C_q^T, G at the last token
+        // Q_g [i][k] (+ Q_g^T), F^T [k][i] (+ F), A^T [j][i], C_q^T
         {
-            const float* glr = sG + (n - 1) * LG;
             for (int idx = tid; idx < BT * 16; idx += PT) {           // rows i, 8 keys per store
                 const int i = idx >> 4, c8 = (idx & 15) * 8;
                 uint32_t pq[4], pk[4];
 #pragma unroll
                 for (int e = 0; e < 8; e += 2) {
                     const int kk = c8 + e;
-                    const float g0 = sG[i * LG + kk], g1 = sG[i * LG + kk + 1];
-                    pq[e / 2] = tc::pack_bf16(scale * __bfloat162float(sQ[i * D + kk]) * exp2f(g0),
-                                              scale * __bfloat162float(sQ[i * D + kk + 1]) * exp2f(g1));
-                    pk[e / 2] = tc::pack_bf16(__bfloat162float(sK[i * D + kk]) * exp2f(glr[kk] - g0),
-                                              __bfloat162float(sK[i * D + kk + 1]) * exp2f(glr[kk + 1] - g1));
+                    const float a0 = sA[i * LG + kk], a1 = sA[i * LG + kk + 1];
+                    pq[e / 2] = tc::pack_bf16(scale * __bfloat162float(sQ[i * D + kk]) * a0 * sC2[kk],
+                                              scale * __bfloat162float(sQ[i * D + kk + 1]) * a1 * sC2[kk + 1]);
+                    if (BWD)
+                        pk[e / 2] = tc::pack_bf16(__bfloat162float(sK[i * D + kk]) * sAL[kk] * __frcp_rn(a0),
+                                                  __bfloat162float(sK[i * D + kk + 1]) * sAL[kk + 1] * __frcp_rn(a1));
                 }
                 *reinterpret_cast<uint4*>(f.QG + ch * BT * D + (size_t)i * D + c8) = make_uint4(pq[0], pq[1], pq[2], pq[3]);
                 if (BWD) *reinterpret_cast<uint4*>(f.KG + ch * BT * D + (size_t)i * D + c8) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
@@ -343,15 +362,16 @@ __global__ void __launch_bounds__(PT, 1)
             for (int idx = tid; idx < D * 8; idx += PT) {             // rows k, 8 tokens per store
                 const int kk = idx >> 3, i8 = (idx & 7) * 8;
                 uint32_t pk[4], pq[4];
+                const float c2 = sC2[kk], al = sAL[kk];
 #pragma unroll
                 for (int e = 0; e < 8; e += 2) {
                     const int i = i8 + e;
-                    const float g0 = sG[i * LG + kk], g1 = sG[(i + 1) * LG + kk];
-                    pk[e / 2] = tc::pack_bf16(__bfloat162float(sK[i * D + kk]) * exp2f(glr[kk] - g0),
-                                              __bfloat162float(sK[(i + 1) * D + kk]) * exp2f(glr[kk] - g1));
+                    const float a0 = sA[i * LG + kk], a1 = sA[(i + 1) * LG + kk];
+                    pk[e / 2] = tc::pack_bf16(__bfloat162float(sK[i * D + kk]) * al * __frcp_rn(a0),
+                                              __bfloat162float(sK[(i + 1) * D + kk]) * al * __frcp_rn(a1));
                     if (BWD)
-                        pq[e / 2] = tc::pack_bf16(scale * __bfloat162float(sQ[i * D + kk]) * exp2f(g0),
-                                                  scale * __bfloat162float(sQ[(i + 1) * D + kk]) * exp2f(g1));
+                        pq[e / 2] = tc::pack_bf16(scale * __bfloat162float(sQ[i * D + kk]) * a0 * c2,
+                                                  scale * __bfloat162float(sQ[(i + 1) * D + kk]) * a1 * c2);
                 }
                 *reinterpret_cast<uint4*>(f.KGT + ch * D * BT + (size_t)kk * BT + i8) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                 if (BWD) *reinterpret_cast<uint4*>(f.QGT + ch * D * BT + (size_t)kk * BT + i8) = make_uint4(pq[0], pq[1], pq[2], pq[3]);
@@ -370,20 +390,20 @@ __global__ void __launch_bounds__(PT, 1)
                     *reinterpret_cast<uint4*>(f.AQKT + ch * BT * BT + (size_t)j * BT + i8) = make_uint4(pc[0], pc[1], pc[2], pc[3]);
                 }
             }
-            if (tid < D) f.GL[ch * D + tid] = glr[tid];
         }
         ok = wait_all(bar, 1, t.err);
         if (ok) {
             tc::fence_after_sync();
             bf16* sW = reinterpret_cast<bf16*>(R1);                     // staged W [64][136]
             float* sU = reinterpret_cast<float*>(R1 + 2 * BT * LW);     // staged U [64][132]
-            const int row = 32 * (warp & 3) + lane;
-            if (warp < 4) {
-                // W^T row = key `row`: W^T[row][i] for the backward, W[i][row] staged
+            const int row = 32 * (warp & 3) + lane, grp = warp >> 2;    // 4 warps per lane quarter
+            // W^T (columns 64..127) by groups 0-1, U^T (columns 128..191) by groups 2-3; 32 columns each
+            const int cbase = (grp & 1) * 32;
+            if (grp < 2) {
 #pragma unroll
-                for (int cb = 0; cb < BT; cb += 16) {
+                for (int cb = cbase; cb < cbase + 32; cb += 16) {
                     float a[16];
-                    tc::tmem_ld16(tc::taddr(tb + 64, 32 * warp, cb), a);
+                    tc::tmem_ld16(tc::taddr(tb + 64, 32 * (warp & 3), cb), a);
                     tc::tmem_wait_ld();
 #pragma unroll
                     for (int jj = 0; jj < 16; ++jj) sW[(cb + jj) * LW + row] = __float2bfloat16_rn(a[jj]);
@@ -398,7 +418,7 @@ __global__ void __launch_bounds__(PT, 1)
                 }
             } else {
 #pragma unroll
-                for (int cb = 0; cb < BT; cb += 16) {
+                for (int cb = cbase; cb < cbase + 32; cb += 16) {
                     float a[16];
                     tc::tmem_ld16(tc::taddr(tb + 128, 32 * (warp & 3), cb), a);
                     tc::tmem_wait_ld();
@@ -642,7 +662,7 @@ __global__ void __launch_bounds__(ST, 1)
     if (warp == 0) tc::tmem_dealloc(tb, 256);
 }
 
-constexpr size_t PREP_SMEM = 65536 + 32768 + sizeof(float) * (BT * LG + 2 * BT * LA + 3 * BC * (BC + 1) + BT + D) +
+constexpr size_t PREP_SMEM = 65536 + 32768 + sizeof(float) * (BT * LG + 2 * BT * LA + 3 * BC * (BC + 1) + BT + 2 * D) +
                              2 * 2 * BT * D + 64 + 1024;
 
 template <int GATE, bool BWD>
