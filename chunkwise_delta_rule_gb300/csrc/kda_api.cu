@@ -78,7 +78,7 @@ Layout layout(const Dims& d) {
             up(4 * chd * D) + up(4 * chd * BT);
     L.ftc = up(2 * chd * BT * D) * 3 + up(2 * chd * BT * BT) + up(4 * chd * BT * D) + up(4 * chd * D) +
             up(4 * chd);
-    L.ftc_b = up(2 * chd * BT * D) * 3 + up(2 * chd * BT * BT) * 2 + up(2 * chd * D * D) + up(2 * chd * BT * D);
+    L.ftc_b = up(2 * chd * BT * BT) + up(2 * chd * D * D) + up(2 * chd * BT * D);
     L.btc = up(2 * chd * D * D) + up(2 * chd * BT * D);
     L.wscr = up(4 * chd * BT * D) * 3 + up(4 * chd * BT * BT) * 2 + up(4 * chd * D) + up(4 * chd * BT);
     return L;
@@ -140,18 +140,14 @@ void carve_fwd_tc(Carver& c, const Dims& d, kda::FwdTC& f, bool bwd_arrays) {
     const size_t chd = (size_t)d.NC * d.H, D = d.D, BT = kda::BT;
     std::memset(&f, 0, sizeof(f));
     f.W = c.take<__nv_bfloat16>(2 * chd * BT * D);
-    f.KGT = c.take<__nv_bfloat16>(2 * chd * BT * D);
+    f.KG = c.take<__nv_bfloat16>(2 * chd * BT * D);
     f.QG = c.take<__nv_bfloat16>(2 * chd * BT * D);
     f.AQK = c.take<__nv_bfloat16>(2 * chd * BT * BT);
     f.U = c.take<float>(4 * chd * BT * D);
     f.GL = c.take<float>(4 * chd * D);
     f.WIDE = c.take<int32_t>(4 * chd);
     if (bwd_arrays) {
-        f.WT = c.take<__nv_bfloat16>(2 * chd * BT * D);
-        f.KG = c.take<__nv_bfloat16>(2 * chd * BT * D);
-        f.QGT = c.take<__nv_bfloat16>(2 * chd * BT * D);
-        f.AQKT = c.take<__nv_bfloat16>(2 * chd * BT * BT);
-        f.AIT = c.take<__nv_bfloat16>(2 * chd * BT * BT);
+        f.AI = c.take<__nv_bfloat16>(2 * chd * BT * BT);
         f.HS = c.take<__nv_bfloat16>(2 * chd * D * D);
         f.R = c.take<__nv_bfloat16>(2 * chd * BT * D);
     }

@@ -54,22 +54,19 @@ struct Bwd {
     float* DBW;   // [NC,H,BT]    <v_i, P_i>
 };
 
-// Chunk intermediates of the tensor-core (bf16 I/O, K = V = 128) path. bf16
-// tiles are stored in the row orders the MMAs read as K-major operands.
+// Chunk intermediates of the tensor-core (bf16 I/O, K = V = 128) path, each
+// stored once in its natural [row][col] layout (the MMAs read them K-major or
+// MN-major as needed).
 struct FwdTC {
     __nv_bfloat16* W;     // [NC,H,BT,D]  W = A E, rows = chunk tokens
-    __nv_bfloat16* KGT;   // [NC,H,D,BT]  F^T (keys decayed to the chunk end), rows = keys
+    __nv_bfloat16* KG;    // [NC,H,BT,D]  F (keys decayed to the chunk end)
     __nv_bfloat16* QG;    // [NC,H,BT,D]  Q_g
     __nv_bfloat16* AQK;   // [NC,H,BT,BT] C_q, rows = receiving token i
     float* U;             // [NC,H,BT,D]  U = A Z
     float* GL;            // [NC,H,D]     cumulative log2-decay at the last token
     int32_t* WIDE;        // [NC,H]       1: gate range too wide for one anchor
-    // backward-only copies (null in the forward)
-    __nv_bfloat16* WT;    // [NC,H,D,BT]
-    __nv_bfloat16* KG;    // [NC,H,BT,D]
-    __nv_bfloat16* QGT;   // [NC,H,D,BT]
-    __nv_bfloat16* AQKT;  // [NC,H,BT,BT] C_q^T
-    __nv_bfloat16* AIT;   // [NC,H,BT,BT] A^T
+    // backward-only (null in the forward)
+    __nv_bfloat16* AI;    // [NC,H,BT,BT] A = (I + L)^-1
     __nv_bfloat16* HS;    // [NC,H,D,D]   state entering the chunk, [key][value]
     __nv_bfloat16* R;     // [NC,H,BT,D]  corrections
 };

@@ -105,7 +105,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     const float x = (j <= i && i < n) ? acc[ii][jj] : 0.f;
                     if (TCOUT) {
                         ft.AQK[ch * BT * BT + i * BT + j] = __float2bfloat16_rn(x);
-                        if (ft.AQKT) ft.AQKT[ch * BT * BT + j * BT + i] = __float2bfloat16_rn(x);
                     } else {
                         AQK[i * BT + j] = x;
                     }
@@ -143,9 +142,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const float kg = sK[r * LD + col] * exp2f(gl[col] - gr);
             if (TCOUT) {
                 ft.QG[ch * BT * D + idx] = __float2bfloat16_rn(qg);
-                ft.KGT[ch * BT * D + (size_t)col * BT + r] = __float2bfloat16_rn(kg);
-                if (ft.QGT) ft.QGT[ch * BT * D + (size_t)col * BT + r] = __float2bfloat16_rn(qg);
-                if (ft.KG) ft.KG[ch * BT * D + idx] = __float2bfloat16_rn(kg);
+                ft.KG[ch * BT * D + idx] = __float2bfloat16_rn(kg);
             } else {
                 f.QG[ch * BT * D + idx] = qg;
                 f.KG[ch * BT * D + idx] = kg;
@@ -155,7 +152,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int idx = tid; idx < BT * BT; idx += NTHREADS) {
             const float a = sAi[(idx / BT) * LA + idx % BT];
             if (TCOUT) {
-                if (ft.AIT) ft.AIT[ch * BT * BT + (size_t)(idx % BT) * BT + idx / BT] = __float2bfloat16_rn(a);
+                if (ft.AI) ft.AI[ch * BT * BT + idx] = __float2bfloat16_rn(a);
             } else {
                 f.AINV[ch * BT * BT + idx] = a;
             }
@@ -186,7 +183,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const int r = TM8::row(ii), cl = TM8::col(jj);
                 if (TCOUT) {
                     ft.W[ch * BT * D + r * D + cl] = __float2bfloat16_rn(acc[ii][jj]);
-                    if (ft.WT) ft.WT[ch * BT * D + (size_t)cl * BT + r] = __float2bfloat16_rn(acc[ii][jj]);
                 } else {
                     f.W[ch * BT * D + r * D + cl] = acc[ii][jj];
                 }

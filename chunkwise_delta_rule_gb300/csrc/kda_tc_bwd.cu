@@ -10,7 +10,8 @@
 // where -R_bar^T W is the residual state term -E^T P supplied once
 // ("ReWY: Faster Backpropagation for Delta-Rule Attention", Algorithm 1 step 5
 // and "Complete Reverse Execution and Boundaries"). S+bar and P of every chunk
-// go to HBM (bf16) for the consumer.
+// go to HBM (bf16) for the consumer. C_q, A, Q_g and W are read as MN-major
+// operands from their natural [token][.] layouts.
 //
 // k_bwd_consumer_tc (a9-a12), one CTA per (chunk slot, head), 256 threads:
 //     [H_q ; -D] = [dO ; P] R^T   (masked: inclusive / strict, sign of D)
@@ -62,11 +63,12 @@ constexpr int B_ADO = 32768;    // dO^T    bf16 [128][64]  16 KB
 constexpr int B_ARB = 49152;    // R_bar^T bf16 [128][64]  16 KB
 constexpr int B_ANR = 65536;    // -R_bar^T                16 KB
 constexpr int B_STAGE = 81920;  // two stages of B operands
-constexpr int S_KG = 0;         // F    [64][128] 16 KB
-constexpr int S_AQT = 16384;    // C_q^T [64][64]  8 KB
-constexpr int S_AIT = 24576;    // A^T  [64][64]   8 KB
-constexpr int S_QGT = 32768;    // Q_g^T [128][64] 16 KB
-constexpr int S_WT = 49152;     // W^T  [128][64] 16 KB
+// B operands in their natural [token][.] layouts: F read K-major, the rest MN-major
+constexpr int S_KG = 0;         // F   [64][128] 16 KB
+constexpr int S_AQ = 16384;     // C_q [64][64]   8 KB
+constexpr int S_AI = 24576;     // A   [64][64]   8 KB
+constexpr int S_QG = 32768;     // Q_g [64][128] 16 KB
+constexpr int S_W = 49152;      // W   [64][128] 16 KB
 constexpr int B_STG = 65536;
 constexpr int B_LAM = B_STAGE + 2 * B_STG;     // lambda [128] fp32
 constexpr int B_TST = B_LAM + 512;             // per-warp transpose staging, 8 x 1280 B
@@ -75,10 +77,10 @@ constexpr int BSCAN_SMEM = B_BAR + 64 + 1024;
 
 __device__ __forceinline__ void bscan_prefetch(uint32_t stg, const FwdTC& f, size_t ch, int tid) {
     load_tile<BT, D, ST>(stg + S_KG, f.KG + ch * BT * D, D, BT, tid);
-    load_tile<BT, BT, ST>(stg + S_AQT, f.AQKT + ch * BT * BT, BT, BT, tid);
-    load_tile<BT, BT, ST>(stg + S_AIT, f.AIT + ch * BT * BT, BT, BT, tid);
-    load_tile<D, BT, ST>(stg + S_QGT, f.QGT + ch * D * BT, BT, D, tid);
-    load_tile<D, BT, ST>(stg + S_WT, f.WT + ch * D * BT, BT, D, tid);
+    load_tile<BT, BT, ST>(stg + S_AQ, f.AQK + ch * BT * BT, BT, BT, tid);
+    load_tile<BT, BT, ST>(stg + S_AI, f.AI + ch * BT * BT, BT, BT, tid);
+    load_tile<BT, D, ST>(stg + S_QG, f.QG + ch * BT * D, D, BT, tid);
+    load_tile<BT, D, ST>(stg + S_W, f.W + ch * BT * D, D, BT, tid);
     tc::cp_async_commit();
 }
 
@@ -178,17 +180,18 @@ __global__ void __launch_bounds__(ST, 1)
         __syncthreads();
         if (tid == 0) {
             tc::fence_after_sync();
-            const uint32_t i64 = tc::idesc_bf16(128, 64), i128 = tc::idesc_bf16(128, 128);
+            const uint32_t i64 = tc::idesc_bf16(128, 64);
+            const uint32_t m64 = tc::idesc_bf16_bmn(128, 64), m128 = tc::idesc_bf16_bmn(128, 128);
 #pragma unroll 1
             for (int ks = 0; ks < 8; ++ks)
                 tc::mma_bf16(tb + 128, tc::sdesc_k(sb + B_ASB, D, ks), tc::sdesc_k(stg + S_KG, BT, ks), i64, ks > 0);
 #pragma unroll 1
             for (int ks = 0; ks < 4; ++ks)
-                tc::mma_bf16(tb + 128, tc::sdesc_k(sb + B_ADO, D, ks), tc::sdesc_k(stg + S_AQT, BT, ks), i64, 1);
+                tc::mma_bf16(tb + 128, tc::sdesc_k(sb + B_ADO, D, ks), tc::sdesc_mn(stg + S_AQ, BT * 128, ks), m64, 1);
             tc::mma_commit(&bar[0]);
 #pragma unroll 1
             for (int ks = 0; ks < 4; ++ks)
-                tc::mma_bf16(tb, tc::sdesc_k(sb + B_ADO, D, ks), tc::sdesc_k(stg + S_QGT, D, ks), i128, 1);
+                tc::mma_bf16(tb, tc::sdesc_k(sb + B_ADO, D, ks), tc::sdesc_mn(stg + S_QG, BT * 128, ks), m128, 1);
         }
         if (c - 1 >= c0) bscan_prefetch(sb + B_STAGE + (stage ^ 1) * B_STG, f, (size_t)(c - 1) * H + h, tid);
         ok = wait_all(&bar[0], ph0, t.err);
@@ -218,14 +221,14 @@ __global__ void __launch_bounds__(ST, 1)
         __syncthreads();
         if (tid == 0) {
             tc::fence_after_sync();
-            const uint32_t i64 = tc::idesc_bf16(128, 64), i128 = tc::idesc_bf16(128, 128);
+            const uint32_t m64 = tc::idesc_bf16_bmn(128, 64), m128 = tc::idesc_bf16_bmn(128, 128);
 #pragma unroll 1
             for (int ks = 0; ks < 4; ++ks)
-                tc::mma_bf16(tb + 192, tc::sdesc_k(sb + B_ARB, D, ks), tc::sdesc_k(stg + S_AIT, BT, ks), i64, ks > 0);
+                tc::mma_bf16(tb + 192, tc::sdesc_k(sb + B_ARB, D, ks), tc::sdesc_mn(stg + S_AI, BT * 128, ks), m64, ks > 0);
             tc::mma_commit(&bar[2]);
 #pragma unroll 1
             for (int ks = 0; ks < 4; ++ks)
-                tc::mma_bf16(tb, tc::sdesc_k(sb + B_ANR, D, ks), tc::sdesc_k(stg + S_WT, D, ks), i128, 1);
+                tc::mma_bf16(tb, tc::sdesc_k(sb + B_ANR, D, ks), tc::sdesc_mn(stg + S_W, BT * 128, ks), m128, 1);
             tc::mma_commit(&bar[1]);
         }
         if (c - 1 >= c0) load_do(c - 1, dnext);

@@ -19,7 +19,8 @@
 //       S^T <- S^T diag(lambda) + R^T F (lambda applied in TMEM, then MMA)
 // ("ReWY" paper, "The chunk system and conventional WY backward"; "Kimi Delta
 // Attention" blog, section 6.4). Operands of chunk c+1 are prefetched with
-// cp.async while chunk c computes.
+// cp.async while chunk c computes; F is read as an MN-major operand from its
+// natural [token][key] layout.
 #include "kda_internal.cuh"
 #include "tc.cuh"
 
@@ -41,12 +42,10 @@ __device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, int32_t
 }
 
 // =========================================================== k_prep_tc
-constexpr int PT = 512;
-constexpr int LG = D + 1;  // padded row stride of fp32 [64 x 128] tiles
+constexpr int PT = 256;     // 8 warps; ~100 KB of shared memory, so two CTAs share an SM
+constexpr int LG = D + 1;   // padded row stride of fp32 [64 x 128] tiles
 constexpr int LA = BT + 1;
 constexpr int LW = D + 8;   // row stride (bf16) of the staged W tile
-constexpr int LU = D + 4;   // row stride (fp32) of the staged U tile
-constexpr int LQ = BT + 8;  // row stride (bf16) of the staged C_q tile
 
 // Blocked inverse of the unit lower-triangular M = I + L (64 x 64, L strict,
 // fp32): the four 16 x 16 diagonal blocks by forward substitution (4 lanes per
@@ -98,26 +97,42 @@ __device__ __forceinline__ void blocked_inverse(const float* sL, float* sA, floa
     }
 }
 
+// Shared-memory map of k_prep_tc (bytes from the 1024-aligned base). The 48 KB
+// operand region OPS is reused phase by phase.
+constexpr int P_OPS = 0;
+constexpr int P_A1 = 0;            // phase 1: [beta K alpha ; s Q alpha] bf16 [128][128]  32 KB
+constexpr int P_B1 = 32768;        //          K / alpha                    bf16 [64][128]   16 KB
+constexpr int P_AKK = 0;           // inverse: L fp32 [64][65]
+constexpr int P_AI = 16640;        //          A fp32 [64][65]
+constexpr int P_T = 33280;         //          merge temporaries [3][16][17]
+constexpr int P_BA = 0;            // phase 2: A bf16 [64][64] (B operand, K = j)       8 KB
+constexpr int P_ET = 8192;         //          E^T bf16 [128][64]                      16 KB
+constexpr int P_ZT = 24576;        //          Z^T bf16 [128][64]                      16 KB
+constexpr int P_W = 0;             // output:  W staged bf16 [64][136]
+constexpr int P_ALPHA = 49152;     // alpha = 2^(G2 - c) fp32 [64][129]
+constexpr int P_K = P_ALPHA + 4 * BT * LG;  // keys bf16 [64][128]
+constexpr int P_MISC = P_K + 2 * BT * D;    // beta [64], 2^c [128], 2^(G2_last - c) [128] (floats)
+constexpr int P_BAR = P_MISC + 4 * (BT + 2 * D);
+constexpr size_t PREP_SMEM = P_BAR + 64 + 1024;
+
 template <int GATE, bool BWD>
-__global__ void __launch_bounds__(PT, 1)
+__global__ void __launch_bounds__(PT, 2)
     k_prep_tc(Shape s, const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* __restrict__ v,
               const bf16* __restrict__ beta, const float* __restrict__ g, Table t, FwdTC f) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                            ~static_cast<uintptr_t>(1023));
-    unsigned char* R1 = base;             // 64 KB operand region (1024-aligned)
-    unsigned char* R2 = R1 + 65536;       // 32 KB operand region
-    float* sA = reinterpret_cast<float*>(R2 + 32768);  // [64][129] G2, then alpha = 2^(G2 - c)
-    bf16* sK = reinterpret_cast<bf16*>(sA + BT * LG);  // [64][128] keys
-    bf16* sQ = sK + BT * D;                             // [64][128] queries
-    float* sAkk = reinterpret_cast<float*>(sQ + BT * D);  // [64][65]
-    float* sAi = sAkk + BT * LA;          // [64][65]
-    float* sT = sAi + BT * LA;            // [3][16][17] merge temporaries
-    float* sBeta = sT + 3 * BC * (BC + 1);  // [64]
-    float* sC2 = sBeta + BT;              // [128] 2^c (c = midpoint anchor of the feature)
-    float* sAL = sC2 + D;                 // [128] 2^(G2_last - c)
-    uint64_t* bar = reinterpret_cast<uint64_t*>(sAL + D);
+    float* sA = reinterpret_cast<float*>(base + P_ALPHA);  // G2, then alpha
+    bf16* sK = reinterpret_cast<bf16*>(base + P_K);
+    float* sBeta = reinterpret_cast<float*>(base + P_MISC);
+    float* sC2 = sBeta + BT;   // 2^c
+    float* sAL = sC2 + D;      // 2^(G2_last - c)
+    float* sAkk = reinterpret_cast<float*>(base + P_AKK);
+    float* sAi = reinterpret_cast<float*>(base + P_AI);
+    float* sT = reinterpret_cast<float*>(base + P_T);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(base + P_BAR);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 1);
+    const uint32_t sb = tc::smem_u32(base);
 
     const int c = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n = t.chunk_len[c];
@@ -142,17 +157,27 @@ __global__ void __launch_bounds__(PT, 1)
             vr4[u] = __ldg(reinterpret_cast<const uint4*>(v + off));
         }
     }
-    float4 gr4[NG];
+    {
+        float4 gr4[NG];
 #pragma unroll
-    for (int u = 0; u < NG; ++u) {
-        const int ci = tid + PT * u, r = ci >> 5, c4 = (ci & 31) * 4;
-        gr4[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (r < n) {
-            if (GATE == 2) gr4[u] = __ldg(reinterpret_cast<const float4*>(g + ((size_t)(tok0 + r) * H + h) * D + c4));
-            if (GATE == 1) {
-                const float x = __ldg(g + (size_t)(tok0 + r) * H + h);
-                gr4[u] = make_float4(x, x, x, x);
+        for (int u = 0; u < NG; ++u) {
+            const int ci = tid + PT * u, r = ci >> 5, c4 = (ci & 31) * 4;
+            gr4[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (r < n) {
+                if (GATE == 2) gr4[u] = __ldg(reinterpret_cast<const float4*>(g + ((size_t)(tok0 + r) * H + h) * D + c4));
+                if (GATE == 1) {
+                    const float x = __ldg(g + (size_t)(tok0 + r) * H + h);
+                    gr4[u] = make_float4(x, x, x, x);
+                }
             }
+        }
+#pragma unroll
+        for (int u = 0; u < NG; ++u) {
+            const int ci = tid + PT * u, r = ci >> 5, c4 = (ci & 31) * 4;
+            sA[r * LG + c4] = gr4[u].x * LOG2E;
+            sA[r * LG + c4 + 1] = gr4[u].y * LOG2E;
+            sA[r * LG + c4 + 2] = gr4[u].z * LOG2E;
+            sA[r * LG + c4 + 3] = gr4[u].w * LOG2E;
         }
     }
     if (tid < BT) sBeta[tid] = (tid < n) ? bfx(beta + (size_t)(tok0 + tid) * H + h) : 0.f;
@@ -160,15 +185,6 @@ __global__ void __launch_bounds__(PT, 1)
     for (int u = 0; u < NU; ++u) {
         const int ci = tid + PT * u, r = ci >> 4, c8 = (ci & 15) * 8;
         *reinterpret_cast<uint4*>(sK + r * D + c8) = kr4[u];
-        *reinterpret_cast<uint4*>(sQ + r * D + c8) = qr4[u];
-    }
-#pragma unroll
-    for (int u = 0; u < NG; ++u) {
-        const int ci = tid + PT * u, r = ci >> 5, c4 = (ci & 31) * 4;
-        sA[r * LG + c4] = gr4[u].x * LOG2E;
-        sA[r * LG + c4 + 1] = gr4[u].y * LOG2E;
-        sA[r * LG + c4 + 2] = gr4[u].z * LOG2E;
-        sA[r * LG + c4 + 3] = gr4[u].w * LOG2E;
     }
     if (tid == 0) {
         tc::mbar_init(bar, 1);
@@ -183,41 +199,36 @@ __global__ void __launch_bounds__(PT, 1)
     tc::fence_after_sync();
     const uint32_t tb = *tslot;
 
-    // a1: cumsum by 4 segments of 16 rows per feature (lanes 4c..4c+3), range, midpoint anchor;
-    // then alpha = 2^(G2 - c) replaces G2 (one exp2 per element; every other decay factor of
-    // this chunk is alpha times a per-feature constant or its reciprocal)
+    // a1: cumsum by 2 segments of 32 rows per feature (lanes 2c, 2c+1), range, midpoint anchor;
+    // alpha = 2^(G2 - c) replaces G2 (one exp2 per element; every decay factor of the chunk is
+    // alpha times a per-feature constant or its reciprocal)
     int wide_col = 0;
-    if (tid < 4 * D) {
-        const int col = tid >> 2, seg = tid & 3;
-        float x[16];
+    {
+        const int col = tid >> 1, seg = tid & 1;
+        float x[32];
         float acc = 0.f;
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            acc += sA[(16 * seg + r) * LG + col];
+        for (int r = 0; r < 32; ++r) {
+            acc += sA[(32 * seg + r) * LG + col];
             x[r] = acc;
         }
-        float pre = __shfl_up_sync(0xffffffffu, acc, 1, 4);
-        if (seg < 1) pre = 0.f;
-        float t2 = __shfl_up_sync(0xffffffffu, acc + pre, 2, 4);
-        if (seg < 2) t2 = 0.f;
-        const float off = pre + t2;  // exclusive prefix of the segment totals
+        float pre = __shfl_up_sync(0xffffffffu, acc, 1, 2);
+        if (seg == 0) pre = 0.f;
         float hi = -INFINITY, lo = INFINITY;
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            x[r] += off;
-            if (16 * seg + r < n) {
+        for (int r = 0; r < 32; ++r) {
+            x[r] += pre;
+            if (32 * seg + r < n) {
                 hi = fmaxf(hi, x[r]);
                 lo = fminf(lo, x[r]);
             }
         }
         hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, 1));
-        hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, 2));
         lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, 1));
-        lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, 2));
         const float cc = 0.5f * (hi + lo);
-        const float glast = __shfl_sync(0xffffffffu, x[15], (lane & ~3) | 3);  // G2 at row 63 = last token
+        const float glast = __shfl_sync(0xffffffffu, x[31], lane | 1);   // G2 at row 63 = last token
 #pragma unroll
-        for (int r = 0; r < 16; ++r) sA[(16 * seg + r) * LG + col] = exp2f(x[r] - cc);
+        for (int r = 0; r < 32; ++r) sA[(32 * seg + r) * LG + col] = exp2f(x[r] - cc);
         if (seg == 0) {
             sC2[col] = exp2f(cc);
             sAL[col] = exp2f(glast - cc);
@@ -229,90 +240,113 @@ __global__ void __launch_bounds__(PT, 1)
     if (tid == 0) f.WIDE[ch] = wide ? 1 : 0;
     bool ok = true;
     if (!wide) {
-        // a2 operands (tf32): A rows 0..63 beta_i k_i alpha_i, rows 64..127 s q_i alpha_i;
-        // B rows j: k_j / alpha_j
-        for (int idx = tid; idx < 2 * BT * 32; idx += PT) {
-            const int r = idx >> 5, cc = idx & 31, i = r & (BT - 1);
-            const bf16* src = (r < BT ? sK : sQ) + i * D + 4 * cc;
-            const float mul = (r < BT) ? sBeta[i] : scale;
-            const float* al = sA + i * LG + 4 * cc;
-            const float4 val = make_float4(mul * __bfloat162float(src[0]) * al[0], mul * __bfloat162float(src[1]) * al[1],
-                                           mul * __bfloat162float(src[2]) * al[2], mul * __bfloat162float(src[3]) * al[3]);
-            *reinterpret_cast<float4*>(R1 + tc::sw128_off(2 * BT, r, cc * 16)) = val;
-        }
-        for (int idx = tid; idx < BT * 32; idx += PT) {
-            const int j = idx >> 5, cc = idx & 31;
-            const bf16* src = sK + j * D + 4 * cc;
-            const float* al = sA + j * LG + 4 * cc;
-            const float4 val = make_float4(__bfloat162float(src[0]) * __frcp_rn(al[0]), __bfloat162float(src[1]) * __frcp_rn(al[1]),
-                                           __bfloat162float(src[2]) * __frcp_rn(al[2]), __bfloat162float(src[3]) * __frcp_rn(al[3]));
-            *reinterpret_cast<float4*>(R2 + tc::sw128_off(BT, j, cc * 16)) = val;
+        // a2 operands (bf16): A rows 0..63 beta_i k_i alpha_i, rows 64..127 s q_i alpha_i; B rows j:
+        // k_j / alpha_j. Q_g = s q alpha 2^c is written from the same registers.
+#pragma unroll
+        for (int u = 0; u < NU; ++u) {
+            const int ci = tid + PT * u, i = ci >> 4, c8 = (ci & 15) * 8;
+            const bf16* kv = reinterpret_cast<const bf16*>(&kr4[u]);
+            const bf16* qv = reinterpret_cast<const bf16*>(&qr4[u]);
+            const float* al = sA + i * LG + c8;
+            const float bt = sBeta[i];
+            uint32_t pe[4], pq[4], pz[4], pg[4];
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+                const float a0 = al[e], a1 = al[e + 1];
+                const float k0 = __bfloat162float(kv[e]), k1 = __bfloat162float(kv[e + 1]);
+                const float q0 = scale * __bfloat162float(qv[e]), q1 = scale * __bfloat162float(qv[e + 1]);
+                pe[e / 2] = tc::pack_bf16(bt * k0 * a0, bt * k1 * a1);
+                pq[e / 2] = tc::pack_bf16(q0 * a0, q1 * a1);
+                pz[e / 2] = tc::pack_bf16(k0 * __frcp_rn(a0), k1 * __frcp_rn(a1));
+                pg[e / 2] = tc::pack_bf16(q0 * a0 * sC2[c8 + e], q1 * a1 * sC2[c8 + e + 1]);
+            }
+            *reinterpret_cast<uint4*>(base + P_A1 + tc::sw128_off(2 * BT, i, c8 * 2)) = make_uint4(pe[0], pe[1], pe[2], pe[3]);
+            *reinterpret_cast<uint4*>(base + P_A1 + tc::sw128_off(2 * BT, BT + i, c8 * 2)) = make_uint4(pq[0], pq[1], pq[2], pq[3]);
+            *reinterpret_cast<uint4*>(base + P_B1 + tc::sw128_off(BT, i, c8 * 2)) = make_uint4(pz[0], pz[1], pz[2], pz[3]);
+            *reinterpret_cast<uint4*>(f.QG + ch * BT * D + (size_t)i * D + c8) = make_uint4(pg[0], pg[1], pg[2], pg[3]);
         }
         tc::fence_async_smem();
         __syncthreads();
         if (tid == 0) {
             tc::fence_after_sync();
-            const uint32_t id = tc::idesc_tf32(128, 64);
-            const uint32_t a0 = tc::smem_u32(R1), b0 = tc::smem_u32(R2);
+            const uint32_t id = tc::idesc_bf16(128, 64);
 #pragma unroll 1
-            for (int st = 0; st < 16; ++st)
-                tc::mma_tf32(tb, tc::sdesc_k(a0, 2 * BT, st), tc::sdesc_k(b0, BT, st), id, st > 0);
+            for (int st = 0; st < 8; ++st)
+                tc::mma_bf16(tb, tc::sdesc_k(sb + P_A1, 2 * BT, st), tc::sdesc_k(sb + P_B1, BT, st), id, st > 0);
             tc::mma_commit(bar);
+        }
+        // F = K 2^(G2_last - G2) = K (2^(G2_last - c)) / alpha, while the MMA runs
+#pragma unroll
+        for (int u = 0; u < NU; ++u) {
+            const int ci = tid + PT * u, i = ci >> 4, c8 = (ci & 15) * 8;
+            const bf16* kv = reinterpret_cast<const bf16*>(&kr4[u]);
+            const float* al = sA + i * LG + c8;
+            uint32_t pk[4];
+#pragma unroll
+            for (int e = 0; e < 8; e += 2)
+                pk[e / 2] = tc::pack_bf16(__bfloat162float(kv[e]) * sAL[c8 + e] * __frcp_rn(al[e]),
+                                          __bfloat162float(kv[e + 1]) * sAL[c8 + e + 1] * __frcp_rn(al[e + 1]));
+            *reinterpret_cast<uint4*>(f.KG + ch * BT * D + (size_t)i * D + c8) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
         ok = wait_all(bar, 0, t.err);
     }
     if (!wide && ok) {
         tc::fence_after_sync();
-        bf16* sAq = reinterpret_cast<bf16*>(R2 + 16384);  // staged C_q [64][72] (transposed copy)
-        // read back [Akk ; Aqk]: warps w, w+4, w+8, w+12 share lanes 32(w%4).., split the 64 columns
+        // read back [Akk ; Aqk]: warps w and w+4 share lanes 32(w%4).., 32 columns each
         {
-            const int row = 32 * (warp & 3) + lane, cb = (warp >> 2) * 16;
-            float a[16];
-            tc::tmem_ld16(tc::taddr(tb, 32 * (warp & 3), cb), a);
+            const int row = 32 * (warp & 3) + lane, cb = (warp >> 2) * 32;
+            float a[32];
+            tc::tmem_ld16(tc::taddr(tb, 32 * (warp & 3), cb), *reinterpret_cast<float(*)[16]>(a));
+            tc::tmem_ld16(tc::taddr(tb, 32 * (warp & 3), cb + 16), *reinterpret_cast<float(*)[16]>(a + 16));
             tc::tmem_wait_ld();
             if (row < BT) {
                 const int i = row;
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) {
+                for (int jj = 0; jj < 32; ++jj) {
                     const int j = cb + jj;
                     sAkk[i * LA + j] = (j < i && i < n) ? a[jj] : 0.f;
                 }
             } else {
                 const int i = row - BT;
-                uint32_t pw[8];
+                uint32_t pw[16];
 #pragma unroll
-                for (int jj = 0; jj < 16; jj += 2) {
+                for (int jj = 0; jj < 32; jj += 2) {
                     const int j = cb + jj;
-                    const float x0 = (j <= i && i < n) ? a[jj] : 0.f;
-                    const float x1 = (j + 1 <= i && i < n) ? a[jj + 1] : 0.f;
-                    pw[jj / 2] = tc::pack_bf16(x0, x1);
-                    if (BWD) {
-                        sAq[i * LQ + j] = __float2bfloat16_rn(x0);
-                        sAq[i * LQ + j + 1] = __float2bfloat16_rn(x1);
-                    }
+                    pw[jj / 2] = tc::pack_bf16((j <= i && i < n) ? a[jj] : 0.f, (j + 1 <= i && i < n) ? a[jj + 1] : 0.f);
                 }
                 uint4* dst = reinterpret_cast<uint4*>(f.AQK + ch * BT * BT + (size_t)i * BT + cb);
-                dst[0] = make_uint4(pw[0], pw[1], pw[2], pw[3]);
-                dst[1] = make_uint4(pw[4], pw[5], pw[6], pw[7]);
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq) dst[qq] = make_uint4(pw[4 * qq], pw[4 * qq + 1], pw[4 * qq + 2], pw[4 * qq + 3]);
             }
         }
         tc::fence_before_sync();
         __syncthreads();
         // a3: A = (I + Akk)^-1
         blocked_inverse(sAkk, sAi, sT, tid);
-        // a4 operands (tf32): R1 <- E^T [128 keys][64 tokens] (beta k 2^G2 = beta k alpha 2^c),
-        // R1+32K <- Z^T [128 values][64 tokens], R2 <- A [64 rows i][64 cols j]
-        for (int idx = tid; idx < D * 16; idx += PT) {
-            const int kr = idx & (D - 1), cc = idx >> 7;
-            float4 val;
-            float* pv = reinterpret_cast<float*>(&val);
-            const float c2 = sC2[kr];
+        // a4: A as the bf16 B operand of W^T = E^T A^T (rows i, K = j); A for the backward
+        for (int idx = tid; idx < BT * 8; idx += PT) {
+            const int i = idx >> 3, j8 = (idx & 7) * 8;
+            const float* ai = sAi + i * LA + j8;
+            uint32_t pw[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int j = 4 * cc + e;
-                pv[e] = sBeta[j] * __bfloat162float(sK[j * D + kr]) * sA[j * LG + kr] * c2;
+            for (int e = 0; e < 4; ++e) pw[e] = tc::pack_bf16(ai[2 * e], ai[2 * e + 1]);
+            const uint4 val = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+            *reinterpret_cast<uint4*>(base + P_BA + tc::sw128_off(BT, i, j8 * 2)) = val;
+            if (BWD) *reinterpret_cast<uint4*>(f.AI + ch * BT * BT + (size_t)i * BT + j8) = val;
+        }
+        __syncthreads();  // A (fp32) consumed: E^T and Z^T may overwrite it
+        // E^T [128 keys][64 tokens] = beta k 2^G2 = beta k alpha 2^c ; Z^T [128 values][64 tokens] = beta v
+        for (int idx = tid; idx < D * 8; idx += PT) {
+            const int kr = idx & (D - 1), j8 = (idx >> 7) * 8;
+            const float c2 = sC2[kr];
+            uint32_t pw[4];
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+                const int j = j8 + e;
+                pw[e / 2] = tc::pack_bf16(sBeta[j] * __bfloat162float(sK[j * D + kr]) * sA[j * LG + kr] * c2,
+                                          sBeta[j + 1] * __bfloat162float(sK[(j + 1) * D + kr]) * sA[(j + 1) * LG + kr] * c2);
             }
-            *reinterpret_cast<float4*>(R1 + tc::sw128_off(D, kr, cc * 16)) = val;
+            *reinterpret_cast<uint4*>(base + P_ET + tc::sw128_off(D, kr, j8 * 2)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
         }
 #pragma unroll
         for (int u = 0; u < NU; ++u) {
@@ -320,120 +354,54 @@ __global__ void __launch_bounds__(PT, 1)
             const bf16* pv = reinterpret_cast<const bf16*>(&vr4[u]);
 #pragma unroll
             for (int e = 0; e < 8; ++e)
-                *reinterpret_cast<float*>(R1 + 32768 + tc::sw128_off(D, c8 + e, j * 4)) = sBeta[j] * __bfloat162float(pv[e]);
-        }
-        for (int idx = tid; idx < BT * 16; idx += PT) {
-            const int i = idx >> 4, cc = idx & 15;
-            const float* ai = sAi + i * LA + 4 * cc;
-            *reinterpret_cast<float4*>(R2 + tc::sw128_off(BT, i, cc * 16)) = make_float4(ai[0], ai[1], ai[2], ai[3]);
+                *reinterpret_cast<bf16*>(base + P_ZT + tc::sw128_off(D, c8 + e, j * 2)) =
+                    __float2bfloat16_rn(sBeta[j] * __bfloat162float(pv[e]));
         }
         tc::fence_async_smem();
         tc::fence_before_sync();
         __syncthreads();
         if (tid == 0) {
             tc::fence_after_sync();
-            const uint32_t id = tc::idesc_tf32(128, 64);
-            const uint32_t a0 = tc::smem_u32(R1), a1 = a0 + 32768, b0 = tc::smem_u32(R2);
+            const uint32_t id = tc::idesc_bf16(128, 64);
 #pragma unroll 1
-            for (int st = 0; st < 8; ++st) tc::mma_tf32(tb + 64, tc::sdesc_k(a0, D, st), tc::sdesc_k(b0, BT, st), id, st > 0);
+            for (int st = 0; st < 4; ++st)
+                tc::mma_bf16(tb + 64, tc::sdesc_k(sb + P_ET, D, st), tc::sdesc_k(sb + P_BA, BT, st), id, st > 0);
 #pragma unroll 1
-            for (int st = 0; st < 8; ++st) tc::mma_tf32(tb + 128, tc::sdesc_k(a1, D, st), tc::sdesc_k(b0, BT, st), id, st > 0);
+            for (int st = 0; st < 4; ++st)
+                tc::mma_bf16(tb + 128, tc::sdesc_k(sb + P_ZT, D, st), tc::sdesc_k(sb + P_BA, BT, st), id, st > 0);
             tc::mma_commit(bar);
-        }
-        // element-wise outputs while the MMAs run, as 16-byte stores:
-        // Q_g [i][k] (+ Q_g^T), F^T [k][i] (+ F), A^T [j][i], C_q^T
-        {
-            for (int idx = tid; idx < BT * 16; idx += PT) {           // rows i, 8 keys per store
-                const int i = idx >> 4, c8 = (idx & 15) * 8;
-                uint32_t pq[4], pk[4];
-#pragma unroll
-                for (int e = 0; e < 8; e += 2) {
-                    const int kk = c8 + e;
-                    const float a0 = sA[i * LG + kk], a1 = sA[i * LG + kk + 1];
-                    pq[e / 2] = tc::pack_bf16(scale * __bfloat162float(sQ[i * D + kk]) * a0 * sC2[kk],
-                                              scale * __bfloat162float(sQ[i * D + kk + 1]) * a1 * sC2[kk + 1]);
-                    if (BWD)
-                        pk[e / 2] = tc::pack_bf16(__bfloat162float(sK[i * D + kk]) * sAL[kk] * __frcp_rn(a0),
-                                                  __bfloat162float(sK[i * D + kk + 1]) * sAL[kk + 1] * __frcp_rn(a1));
-                }
-                *reinterpret_cast<uint4*>(f.QG + ch * BT * D + (size_t)i * D + c8) = make_uint4(pq[0], pq[1], pq[2], pq[3]);
-                if (BWD) *reinterpret_cast<uint4*>(f.KG + ch * BT * D + (size_t)i * D + c8) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            }
-            for (int idx = tid; idx < D * 8; idx += PT) {             // rows k, 8 tokens per store
-                const int kk = idx >> 3, i8 = (idx & 7) * 8;
-                uint32_t pk[4], pq[4];
-                const float c2 = sC2[kk], al = sAL[kk];
-#pragma unroll
-                for (int e = 0; e < 8; e += 2) {
-                    const int i = i8 + e;
-                    const float a0 = sA[i * LG + kk], a1 = sA[(i + 1) * LG + kk];
-                    pk[e / 2] = tc::pack_bf16(__bfloat162float(sK[i * D + kk]) * al * __frcp_rn(a0),
-                                              __bfloat162float(sK[(i + 1) * D + kk]) * al * __frcp_rn(a1));
-                    if (BWD)
-                        pq[e / 2] = tc::pack_bf16(scale * __bfloat162float(sQ[i * D + kk]) * a0 * c2,
-                                                  scale * __bfloat162float(sQ[(i + 1) * D + kk]) * a1 * c2);
-                }
-                *reinterpret_cast<uint4*>(f.KGT + ch * D * BT + (size_t)kk * BT + i8) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                if (BWD) *reinterpret_cast<uint4*>(f.QGT + ch * D * BT + (size_t)kk * BT + i8) = make_uint4(pq[0], pq[1], pq[2], pq[3]);
-            }
-            if (BWD) {
-                for (int idx = tid; idx < BT * 8; idx += PT) {        // rows j of A^T and C_q^T
-                    const int j = idx >> 3, i8 = (idx & 7) * 8;
-                    uint32_t pa[4], pc[4];
-#pragma unroll
-                    for (int e = 0; e < 8; e += 2) {
-                        pa[e / 2] = tc::pack_bf16(sAi[(i8 + e) * LA + j], sAi[(i8 + e + 1) * LA + j]);
-                        pc[e / 2] = (uint32_t)(*reinterpret_cast<const uint16_t*>(&sAq[(i8 + e) * LQ + j])) |
-                                    ((uint32_t)(*reinterpret_cast<const uint16_t*>(&sAq[(i8 + e + 1) * LQ + j])) << 16);
-                    }
-                    *reinterpret_cast<uint4*>(f.AIT + ch * BT * BT + (size_t)j * BT + i8) = make_uint4(pa[0], pa[1], pa[2], pa[3]);
-                    *reinterpret_cast<uint4*>(f.AQKT + ch * BT * BT + (size_t)j * BT + i8) = make_uint4(pc[0], pc[1], pc[2], pc[3]);
-                }
-            }
         }
         ok = wait_all(bar, 1, t.err);
         if (ok) {
             tc::fence_after_sync();
-            bf16* sW = reinterpret_cast<bf16*>(R1);                     // staged W [64][136]
-            float* sU = reinterpret_cast<float*>(R1 + 2 * BT * LW);     // staged U [64][132]
-            const int row = 32 * (warp & 3) + lane, grp = warp >> 2;    // 4 warps per lane quarter
-            // W^T (columns 64..127) by groups 0-1, U^T (columns 128..191) by groups 2-3; 32 columns each
-            const int cbase = (grp & 1) * 32;
-            if (grp < 2) {
+            bf16* sW = reinterpret_cast<bf16*>(base + P_W);   // staged W [64][136]
+            const int row = 32 * (warp & 3) + lane;
+            if (warp < 4) {
+                // W^T row = key `row` -> staged W[i][row]
 #pragma unroll
-                for (int cb = cbase; cb < cbase + 32; cb += 16) {
+                for (int cb = 0; cb < BT; cb += 16) {
                     float a[16];
-                    tc::tmem_ld16(tc::taddr(tb + 64, 32 * (warp & 3), cb), a);
+                    tc::tmem_ld16(tc::taddr(tb + 64, 32 * warp, cb), a);
                     tc::tmem_wait_ld();
 #pragma unroll
                     for (int jj = 0; jj < 16; ++jj) sW[(cb + jj) * LW + row] = __float2bfloat16_rn(a[jj]);
-                    if (BWD) {
-                        uint32_t pw[8];
-#pragma unroll
-                        for (int jj = 0; jj < 8; ++jj) pw[jj] = tc::pack_bf16(a[2 * jj], a[2 * jj + 1]);
-                        uint4* dst = reinterpret_cast<uint4*>(f.WT + ch * D * BT + (size_t)row * BT + cb);
-                        dst[0] = make_uint4(pw[0], pw[1], pw[2], pw[3]);
-                        dst[1] = make_uint4(pw[4], pw[5], pw[6], pw[7]);
-                    }
                 }
             } else {
+                // U^T row = value `row` -> U[i][row] (fp32, coalesced over the value index)
+                float* U = f.U + ch * BT * D + row;
 #pragma unroll
-                for (int cb = cbase; cb < cbase + 32; cb += 16) {
+                for (int cb = 0; cb < BT; cb += 16) {
                     float a[16];
                     tc::tmem_ld16(tc::taddr(tb + 128, 32 * (warp & 3), cb), a);
                     tc::tmem_wait_ld();
 #pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) sU[(cb + jj) * LU + row] = a[jj];
+                    for (int jj = 0; jj < 16; ++jj) U[(size_t)(cb + jj) * D] = a[jj];
                 }
             }
             __syncthreads();
             for (int idx = tid; idx < BT * 16; idx += PT) {
                 const int i = idx >> 4, c8 = (idx & 15) * 8;
                 *reinterpret_cast<uint4*>(f.W + ch * BT * D + (size_t)i * D + c8) = *reinterpret_cast<const uint4*>(sW + i * LW + c8);
-            }
-            for (int idx = tid; idx < BT * 32; idx += PT) {
-                const int i = idx >> 5, c4 = (idx & 31) * 4;
-                *reinterpret_cast<float4*>(f.U + ch * BT * D + (size_t)i * D + c4) = *reinterpret_cast<const float4*>(sU + i * LU + c4);
             }
         }
     }
@@ -450,7 +418,7 @@ constexpr int OFF_AS = 0;                    // S^T bf16 [128][128]   32 KB
 constexpr int OFF_AR = OFF_AS + 32768;       // R^T bf16 [128][64]    16 KB
 constexpr int OFF_STAGE = OFF_AR + 16384;    // two stages
 constexpr int STG_W = 0;                     // W   [64][128]  16 KB
-constexpr int STG_KG = 16384;                // F^T [128][64]  16 KB
+constexpr int STG_KG = 16384;                // F   [64][128]  16 KB (read MN-major)
 constexpr int STG_QG = 32768;                // Q_g [64][128]  16 KB
 constexpr int STG_AQ = 49152;                // C_q [64][64]    8 KB
 constexpr int STG_BYTES = 57344;
@@ -476,7 +444,7 @@ __device__ __forceinline__ void load_tile(uint32_t sbase, const bf16* src, int t
 template <int MODE>
 __device__ __forceinline__ void fscan_prefetch(uint32_t stg, const FwdTC& f, size_t ch, int tid) {
     load_tile<BT, D>(stg + STG_W, f.W + ch * BT * D, tid);
-    load_tile<D, BT>(stg + STG_KG, f.KGT + ch * D * BT, tid);
+    load_tile<BT, D>(stg + STG_KG, f.KG + ch * BT * D, tid);
     if (MODE & 1) {
         load_tile<BT, D>(stg + STG_QG, f.QG + ch * BT * D, tid);
         load_tile<BT, BT>(stg + STG_AQ, f.AQK + ch * BT * BT, tid);
@@ -619,7 +587,7 @@ __global__ void __launch_bounds__(ST, 1)
             }
 #pragma unroll 1
             for (int ks = 0; ks < 4; ++ks)
-                tc::mma_bf16(tb, tc::sdesc_k(aR, D, ks), tc::sdesc_k(stg + STG_KG, D, ks), tc::idesc_bf16(128, 128), 1);
+                tc::mma_bf16(tb, tc::sdesc_k(aR, D, ks), tc::sdesc_mn(stg + STG_KG, BT * 128, ks), tc::idesc_bf16_bmn(128, 128), 1);
             tc::mma_commit(&bar[1]);
         }
         // 5. output rows of this value column
@@ -662,8 +630,6 @@ __global__ void __launch_bounds__(ST, 1)
     if (warp == 0) tc::tmem_dealloc(tb, 256);
 }
 
-constexpr size_t PREP_SMEM = 65536 + 32768 + sizeof(float) * (BT * LG + 2 * BT * LA + 3 * BC * (BC + 1) + BT + 2 * D) +
-                             2 * 2 * BT * D + 64 + 1024;
 
 template <int GATE, bool BWD>
 cudaError_t run_prep(const Shape& s, const void* q, const void* k, const void* v, const void* beta,

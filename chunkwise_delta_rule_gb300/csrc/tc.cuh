@@ -48,10 +48,28 @@ __device__ __forceinline__ uint64_t sdesc_k(uint32_t saddr, int R, int s) {
     return sdesc(saddr + (uint32_t)((s >> 2) * R * 128 + (s & 3) * 32));
 }
 
+// Shared-memory descriptor of an MN-major operand in the 128-byte swizzle
+// layout: rows are K indices (128 bytes of MN each, swizzled exactly like a
+// K-major tile with R = K rows), 8-row K groups 1024 bytes apart (SBO),
+// 64-element MN atoms `atom_stride` bytes apart (LBO). k-step s (16 K rows of
+// bf16) starts 2048 bytes further.
+__device__ __forceinline__ uint64_t sdesc_mn(uint32_t saddr, uint32_t atom_stride, int s) {
+    const uint32_t a = saddr + (uint32_t)s * 2048u;
+    uint64_t d = 0;
+    d |= (uint64_t)((a & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((atom_stride >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)(1024u >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
 // Instruction descriptors (dense, fp32 accumulator, K-major A and B).
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
+// bf16, K-major A, MN-major B.
+__host__ __device__ constexpr uint32_t idesc_bf16_bmn(int M, int N) { return idesc_bf16(M, N) | (1u << 16); }
 __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
     return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }

@@ -67,7 +67,7 @@ def test_workspace_size_arithmetic():
     ptc = _prob(io=0)
     ftc = up(2 * chd * BT * D) * 3 + up(2 * chd * BT * BT) + up(4 * chd * BT * D) + up(4 * chd * D) + up(4 * chd)
     assert _ws(ptc, 0) == table + ftc
-    ftc_b = up(2 * chd * BT * D) * 3 + up(2 * chd * BT * BT) * 2 + up(2 * chd * D * D) + up(2 * chd * BT * D)
+    ftc_b = up(2 * chd * BT * BT) + up(2 * chd * D * D) + up(2 * chd * BT * D)
     btc = up(2 * chd * D * D) + up(2 * chd * BT * D)
     wscr = up(4 * chd * BT * D) * 3 + up(4 * chd * BT * BT) * 2 + up(4 * chd * D) + up(4 * chd * BT)
     assert _ws(ptc, 1) == table + ftc + ftc_b + btc + wscr
