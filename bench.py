@@ -74,22 +74,40 @@ def flops_model(case):
 
 
 def kernel_work(case):
-    """Algorithmic FLOPs per launch of each library kernel (same model, split
-    by the products each kernel owns)."""
+    """Algorithmic work per launch of each library kernel: dense FLOPs (the
+    products the kernel owns in the FLOP model) and bytes (every tensor the
+    kernel must read or write once, at its stored precision), summed over
+    chunk x head with the exact chunk length n (d = dk = dv)."""
     d = case.K
-    w = {}
-    acc = dict(k_prep=0.0, k_fwd_scan=0.0, k_fwd_scan_recompute=0.0, k_bwd_scan=0.0,
-               k_bwd_dstate=0.0, k_bwd_intra=0.0)
+    e = 2 if case.io == "bf16" else 4
+    gb = {"channel": 4 * d, "scalar": 4, "none": 0}[case.gate]   # log-decay bytes per token
+    fl = dict(k_prep=0.0, k_fwd_scan=0.0, k_fwd_scan_recompute=0.0, k_bwd_scan=0.0,
+              k_bwd_dstate=0.0, k_bwd_intra=0.0, k_prep_tc=0.0, k_fwd_scan_tc=0.0,
+              k_fwd_scan_tc_recompute=0.0, k_bwd_scan_tc=0.0, k_bwd_consumer_tc=0.0)
+    by = dict.fromkeys(fl, 0.0)
     for n in chunk_lengths(case):
-        acc["k_prep"] += 8 * n * n * d + 2 * n ** 3 / 3
-        acc["k_fwd_scan"] += 6 * n * d * d + 2 * n * n * d
-        acc["k_fwd_scan_recompute"] += 4 * n * d * d
-        acc["k_bwd_scan"] += 6 * n * d * d + 4 * n * n * d
-        acc["k_bwd_dstate"] += 4 * n * n * d + 6 * n * d * d
-        acc["k_bwd_intra"] += 8 * n * n * d
-    for k, v in acc.items():
-        w[k] = v * case.H
-    return w
+        fl["k_prep"] += 8 * n * n * d + 2 * n ** 3 / 3
+        fl["k_fwd_scan"] += 6 * n * d * d + 2 * n * n * d
+        fl["k_fwd_scan_recompute"] += 4 * n * d * d
+        fl["k_bwd_scan"] += 6 * n * d * d + 4 * n * n * d
+        fl["k_bwd_dstate"] += 4 * n * n * d + 6 * n * d * d
+        fl["k_bwd_intra"] += 8 * n * n * d
+        fl["k_prep_tc"] += 8 * n * n * d + 2 * n ** 3 / 3
+        fl["k_fwd_scan_tc"] += 6 * n * d * d + 2 * n * n * d
+        fl["k_fwd_scan_tc_recompute"] += 4 * n * d * d
+        fl["k_bwd_scan_tc"] += 6 * n * d * d + 4 * n * n * d
+        fl["k_bwd_consumer_tc"] += 12 * n * n * d + 6 * n * d * d
+        # tensor-core path: bf16 tiles W, F, Q_g, C_q, A, S, S+bar, R, P; fp32 U and G at the chunk end
+        by["k_prep_tc"] += 3 * n * d * e + n * gb + n * e + 3 * n * d * 2 + n * n * 2 + n * d * 4 + d * 4
+        by["k_fwd_scan_tc"] += 3 * n * d * 2 + n * n * 2 + n * d * 4 + d * 4 + n * d * e
+        by["k_fwd_scan_tc_recompute"] += 2 * n * d * 2 + n * d * 4 + d * 4 + d * d * 2 + n * d * 2
+        by["k_bwd_scan_tc"] += 3 * n * d * 2 + 2 * n * n * 2 + d * 4 + n * d * e + d * d * 2 + n * d * 2
+        by["k_bwd_consumer_tc"] += (3 * n * d * 2 + 2 * d * d * 2 + 3 * n * d * e + n * gb + n * e
+                                    + 3 * n * d * e + n * e + n * gb)
+    st = 2 * 4 * d * d * case.N   # initial/final state (or its adjoint) per sequence, read + write
+    for kname in ("k_fwd_scan_tc", "k_bwd_scan_tc"):
+        by[kname] += st
+    return {k: (fl[k] * case.H, by[k] * case.H) for k in fl}
 
 
 def token_bytes(case):
@@ -310,18 +328,41 @@ def run_ours(args):
     if dom:
         n_l, tot = kern[dom]
         avg_ms = tot / n_l
-        fl = work.get(dom, 0.0)
+        fl, by = work.get(dom, (0.0, 0.0))
         sm_mhz = clk["sm_mhz"] if clk else pk["sm_max"]
-        alu_peak = 152 * 128 * 2 * pk["sm_max"] * 1e6 / 1e12   # FP32 FMA lanes x 2 x clock
-        achieved = fl / (avg_ms * 1e-3) / 1e12
-        roof = {"kernel": dom, "bound": "alu", "achieved": round(achieved, 3),
-                "peak": round(alu_peak, 1), "unit": "TFLOP/s", "frac": round(achieved / alu_peak, 4),
-                "traffic": traffic_for(dom), "avg_launch_ms": round(avg_ms, 4),
-                "note": "fp32 CUDA-core FMA kernel; peak = 152 SMs x 128 FP32 lanes x 2 x max SM clock",
-                "sm_mhz_under_load": sm_mhz}
-    kernels = {k: {"launches": v[0], "avg_ms": round(v[1] / v[0], 4),
-                   "share": round(v[1] / max(sum(x[1] for x in kern.values()), 1e-9), 4)}
-               for k, v in kern.items()}
+        if dom.endswith("_tc") or dom.endswith("_tc_recompute"):
+            # which roofline binds: compare the kernel's time at either peak
+            t_hbm = by / (pk["hbm"] * 1e9)
+            t_tc = fl / (pk["bf16"] * 1e12)
+            if t_hbm >= t_tc:
+                achieved = by / (avg_ms * 1e-3) / 1e9
+                roof = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm"],
+                        "unit": "GB/s", "frac": round(achieved / pk["hbm"], 4)}
+            else:
+                achieved = fl / (avg_ms * 1e-3) / 1e12
+                roof = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 2), "peak": pk["bf16"],
+                        "unit": "TFLOP/s", "frac": round(achieved / pk["bf16"], 4)}
+            roof.update({"traffic": traffic_for(dom), "avg_launch_ms": round(avg_ms, 4),
+                         "algorithmic_bytes": by, "algorithmic_flops": fl,
+                         "tensor_frac_of_bf16_peak": round(fl / (avg_ms * 1e-3) / 1e12 / pk["bf16"], 4),
+                         "peak_source": pk["source"] + " (MEASURED_PEAKS.json)", "sm_mhz_under_load": sm_mhz})
+        else:
+            alu_peak = 152 * 128 * 2 * pk["sm_max"] * 1e6 / 1e12   # FP32 FMA lanes x 2 x clock
+            achieved = fl / (avg_ms * 1e-3) / 1e12
+            roof = {"kernel": dom, "bound": "alu", "achieved": round(achieved, 3),
+                    "peak": round(alu_peak, 1), "unit": "TFLOP/s", "frac": round(achieved / alu_peak, 4),
+                    "traffic": traffic_for(dom), "avg_launch_ms": round(avg_ms, 4),
+                    "note": "fp32 CUDA-core FMA kernel; peak = 152 SMs x 128 FP32 lanes x 2 x max SM clock",
+                    "sm_mhz_under_load": sm_mhz}
+    kernels = {}
+    for k, v in kern.items():
+        rec = {"launches": v[0], "avg_ms": round(v[1] / v[0], 4),
+               "share": round(v[1] / max(sum(x[1] for x in kern.values()), 1e-9), 4)}
+        if k in work and work[k][1] > 0:
+            gbs = work[k][1] / (v[1] / v[0] * 1e-3) / 1e9
+            rec.update({"algorithmic_gbs": round(gbs, 1), "hbm_frac": round(gbs / pk["hbm"], 4),
+                        "tflops": round(work[k][0] / (v[1] / v[0] * 1e-3) / 1e12, 2)})
+        kernels[k] = rec
 
     e2e = None
     if not args.no_e2e:

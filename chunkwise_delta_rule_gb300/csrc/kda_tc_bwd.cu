@@ -158,11 +158,14 @@ __global__ void __launch_bounds__(ST, 1)
         __syncthreads();
         // S+bar^T -> bf16 operand and HBM; then S_bar^T <- S+bar^T diag(lambda)
         bf16* SBP = b.SBP + ch * D * D;
-#pragma unroll 1
-        for (int cb = kb; cb < kb + 64; cb += 16) {
-            float a[16];
-            tc::tmem_ld16(tl + cb, a);
-            tc::tmem_wait_ld();
+        float sv[4][16];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) tc::tmem_ld16(tl + kb + 16 * q4, sv[q4]);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+            const int cb = kb + 16 * q4;
+            float (&a)[16] = sv[q4];
             uint32_t pw[8];
 #pragma unroll
             for (int jj = 0; jj < 8; ++jj) pw[jj] = tc::pack_bf16(a[2 * jj], a[2 * jj + 1]);
@@ -199,11 +202,13 @@ __global__ void __launch_bounds__(ST, 1)
         if (!ok) break;
         tc::fence_after_sync();
         // R_bar^T -> bf16 operands (and its negation), this thread's half of the rows
+        float rv[2][16];
+        tc::tmem_ld16(tl + 128 + ib, rv[0]);
+        tc::tmem_ld16(tl + 128 + ib + 16, rv[1]);
+        tc::tmem_wait_ld();
 #pragma unroll
         for (int cq = 0; cq < 32; cq += 16) {
-            float a[16];
-            tc::tmem_ld16(tl + 128 + ib + cq, a);
-            tc::tmem_wait_ld();
+            float (&a)[16] = rv[cq / 16];
             uint32_t pw[8], nw[8];
 #pragma unroll
             for (int jj = 0; jj < 8; ++jj) {
@@ -237,12 +242,13 @@ __global__ void __launch_bounds__(ST, 1)
         if (!ok) break;
         tc::fence_after_sync();
         bf16* P = b.P + ch * BT * D;
-#pragma unroll 1
-        for (int cq = 0; cq < 32; cq += 16) {
-            float a[16];
-            tc::tmem_ld16(tl + 192 + ib + cq, a);
+        {
+            float pv[2][16];
+            tc::tmem_ld16(tl + 192 + ib, pv[0]);
+            tc::tmem_ld16(tl + 192 + ib + 16, pv[1]);
             tc::tmem_wait_ld();
-            tc::warp_store_t16(tst, a, P + (size_t)(ib + cq) * D + 32 * quad, D, 16, lane);
+            tc::warp_store_t16(tst, pv[0], P + (size_t)ib * D + 32 * quad, D, 16, lane);
+            tc::warp_store_t16(tst, pv[1], P + (size_t)(ib + 16) * D + 32 * quad, D, 16, lane);
         }
         tc::fence_before_sync();
         ok = wait_all(&bar[1], ph1, t.err);

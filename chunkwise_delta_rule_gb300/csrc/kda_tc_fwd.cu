@@ -514,12 +514,16 @@ __global__ void __launch_bounds__(ST, 1)
         for (int i = 0; i < 32; ++i) u[i] = U[(size_t)i * D];
         if (tid < D) sLam[tid] = exp2f(f.GL[ch * D + tid]);
         __syncthreads();
-        // 1. S^T -> bf16 operand (and the saved state), then S^T <- S^T diag(lambda)
-#pragma unroll 1
-        for (int cb = kb; cb < kb + 64; cb += 16) {
-            float a[16];
-            tc::tmem_ld16(tl + cb, a);
-            tc::tmem_wait_ld();
+        // 1. S^T -> bf16 operand (and the saved state), then S^T <- S^T diag(lambda);
+        //    the four TMEM loads are issued before a single wait
+        float sv[4][16];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) tc::tmem_ld16(tl + kb + 16 * q4, sv[q4]);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+            const int cb = kb + 16 * q4;
+            float (&a)[16] = sv[q4];
             uint32_t pw[8];
 #pragma unroll
             for (int jj = 0; jj < 8; ++jj) pw[jj] = tc::pack_bf16(a[2 * jj], a[2 * jj + 1]);
@@ -557,11 +561,13 @@ __global__ void __launch_bounds__(ST, 1)
         if (!ok) break;
         tc::fence_after_sync();
         // 3. R^T = U^T - D1 (bf16 operand; saved for the backward)
+        float rv[2][16];
+        tc::tmem_ld16(tl + 128 + ib, rv[0]);
+        tc::tmem_ld16(tl + 128 + ib + 16, rv[1]);
+        tc::tmem_wait_ld();
 #pragma unroll
         for (int cq = 0; cq < 32; cq += 16) {
-            float a[16];
-            tc::tmem_ld16(tl + 128 + ib + cq, a);
-            tc::tmem_wait_ld();
+            float (&a)[16] = rv[cq / 16];
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) a[jj] = u[cq + jj] - a[jj];
             uint32_t pw[8];
@@ -596,15 +602,16 @@ __global__ void __launch_bounds__(ST, 1)
             ph2 ^= 1;
             if (!ok) break;
             tc::fence_after_sync();
-#pragma unroll 1
+            float ov[2][16];
+            tc::tmem_ld16(tl + 192 + ib, ov[0]);
+            tc::tmem_ld16(tl + 192 + ib + 16, ov[1]);
+            tc::tmem_wait_ld();
+#pragma unroll
             for (int cq = 0; cq < 32; cq += 16) {
                 const int r0 = ib + cq;
-                if (r0 >= len) break;
-                float a[16];
-                tc::tmem_ld16(tl + 192 + r0, a);
-                tc::tmem_wait_ld();
-                tc::warp_store_t16(tst, a, o + ((size_t)(tok0 + r0) * H + h) * D + 32 * quad, (size_t)H * D,
-                                   len - r0, lane);
+                if (r0 < len)
+                    tc::warp_store_t16(tst, ov[cq / 16], o + ((size_t)(tok0 + r0) * H + h) * D + 32 * quad,
+                                       (size_t)H * D, len - r0, lane);
             }
             tc::fence_before_sync();
         }
