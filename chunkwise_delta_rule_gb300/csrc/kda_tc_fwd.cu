@@ -4,12 +4,14 @@
 //   G2 = in-chunk cumsum of g / ln 2; one anchor c per feature (the midpoint
 //   of the chunk's range) so that
 //       [Akk ; Aqk] = [beta K 2^(G2-c) ; s Q 2^(G2-c)] (K 2^(c-G2))^T
-//   is a single M = 128, N = 64, K = 128 tf32 MMA ("Kimi Delta Attention"
+//   is a single M = 128, N = 64, K = 128 bf16 MMA ("Kimi Delta Attention"
 //   blog, sections 6.3 and 6.5; "ReWY" paper, centered factors); strict /
 //   inclusive masks on the TMEM read-back; A = (I + Akk)^-1 in fp32 by
-//   forward substitution; W^T = E^T A^T and U^T = Z^T A^T as two M = 128 tf32
-//   MMAs. A chunk whose gate range exceeds 2^80 is left to the CUDA-core prep
-//   (flag WIDE), which anchors per 16-token sub-chunk instead.
+//   forward substitution in registers; W^T = (E'^T A^T) diag(2^c) and
+//   U^T = V^T (A diag(beta))^T as M = 128 bf16 MMAs whose A operands E' =
+//   beta K alpha (already in shared memory for the first MMA) and V are read
+//   MN-major. A chunk whose gate range exceeds 2^80 is left to the CUDA-core
+//   prep (flag WIDE), which anchors per 16-token sub-chunk instead.
 //
 // k_fwd_scan_tc, one CTA per (sequence, head), 128 threads, thread v owns
 // value column v (TMEM lane v). The transposed state S^T (V x K, fp32) stays
@@ -43,77 +45,61 @@ __device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, int32_t
 
 // =========================================================== k_prep_tc
 constexpr int PT = 256;     // 8 warps; ~100 KB of shared memory, so two CTAs share an SM
-constexpr int LG = D + 1;   // padded row stride of fp32 [64 x 128] tiles
-constexpr int LA = BT + 1;
+constexpr int LG = D + 4;   // fp32 row stride of the G2 / alpha tile (16-byte aligned rows)
 constexpr int LW = D + 8;   // row stride (bf16) of the staged W tile
 
-// Blocked inverse of the unit lower-triangular M = I + L (64 x 64, L strict,
-// fp32): the four 16 x 16 diagonal blocks by forward substitution (4 lanes per
-// column), then the off-diagonal blocks level by level,
-//     A_ij = -A_ii * sum_{m=j}^{i-1} L_im A_mj,
-// the 4 x 4 block merge of the GatedDeltaNet-2 spec transcription (section 2.4).
-__device__ __forceinline__ void blocked_inverse(const float* sL, float* sA, float* sT, int tid) {
-    if (tid < 4 * BT) {  // whole warps: 64 threads per diagonal block, 4 lanes per column
-        const int blk = tid >> 6, col = (tid >> 2) & 15, part = tid & 3;
-        const int o = blk * BC;
-        for (int r = part; r < BT; r += 4) sA[r * LA + o + col] = 0.f;
-        for (int r = part; r < BC; r += 4) sA[(o + r) * LA + o + col] = (r == col) ? 1.f : 0.f;
-        __syncwarp();
-        for (int i = 1; i < BC; ++i) {
-            float acc = 0.f;
-            if (i > col)
-                for (int j = col + part; j < i; j += 4) acc = fmaf(sL[(o + i) * LA + o + j], sA[(o + j) * LA + o + col], acc);
-            acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-            acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-            if (part == 0 && i > col) sA[(o + i) * LA + o + col] = -acc;
-            __syncwarp();
+// A = (I + L)^-1 for the strictly lower 64 x 64 L, given as L^T (fp32, row m
+// holds column m of L), by forward substitution on row vectors,
+//     A_i = e_i - sum_{m<i} L_im A_m,
+// applied right-looking: once row m of A is final it is broadcast and every
+// later row subtracts L_im A_m. Warp w owns the columns 8w..8w+7 (rows of A
+// have zeros left of the diagonal, so the warp starts at pivot 8w), lane l
+// the rows l and l + 32. No block-level synchronisation.
+__device__ __forceinline__ void inverse_rows(const float* sLt, int warp, int lane, float (&x0)[8], float (&x1)[8]) {
+    const int cb = 8 * warp;
+#pragma unroll
+    for (int cc = 0; cc < 8; ++cc) {
+        x0[cc] = (lane == cb + cc) ? 1.f : 0.f;
+        x1[cc] = (lane + 32 == cb + cc) ? 1.f : 0.f;
+    }
+#pragma unroll 1
+    for (int m = cb; m < 32; ++m) {
+        const float l0 = sLt[m * BT + lane], l1 = sLt[m * BT + 32 + lane];
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+            const float p = __shfl_sync(0xffffffffu, x0[cc], m);
+            x0[cc] = fmaf(-l0, p, x0[cc]);
+            x1[cc] = fmaf(-l1, p, x1[cc]);
         }
     }
-    __syncthreads();
-    for (int lvl = 1; lvl < BT / BC; ++lvl) {
-        const int nb = BT / BC - lvl;  // blocks (i, j = i - lvl) on this level
-        // T_ij = sum_{m=j}^{i-1} L_im A_mj
-        for (int idx = tid; idx < nb * BC * BC; idx += PT) {
-            const int b = idx >> 8, r = (idx >> 4) & 15, cc = idx & 15;
-            const int j = b, i = b + lvl;
-            float acc = 0.f;
-            for (int m = j; m < i; ++m)
+    // pivots 32..62 touch only the rows l + 32 (L_lm = 0 for l < 32 <= m)
+#pragma unroll 1
+    for (int m = (cb > 32 ? cb : 32); m < BT - 1; ++m) {
+        const float l1 = sLt[m * BT + 32 + lane];
 #pragma unroll
-                for (int x = 0; x < BC; ++x)
-                    acc = fmaf(sL[(i * BC + r) * LA + m * BC + x], sA[(m * BC + x) * LA + j * BC + cc], acc);
-            sT[(b * BC + r) * (BC + 1) + cc] = acc;
+        for (int cc = 0; cc < 8; ++cc) {
+            const float p = __shfl_sync(0xffffffffu, x1[cc], m - 32);
+            x1[cc] = fmaf(-l1, p, x1[cc]);
         }
-        __syncthreads();
-        // A_ij = -A_ii T_ij
-        for (int idx = tid; idx < nb * BC * BC; idx += PT) {
-            const int b = idx >> 8, r = (idx >> 4) & 15, cc = idx & 15;
-            const int j = b, i = b + lvl;
-            float acc = 0.f;
-#pragma unroll
-            for (int x = 0; x < BC; ++x) acc = fmaf(sA[(i * BC + r) * LA + i * BC + x], sT[(b * BC + x) * (BC + 1) + cc], acc);
-            sA[(i * BC + r) * LA + j * BC + cc] = -acc;
-        }
-        __syncthreads();
     }
 }
 
-// Shared-memory map of k_prep_tc (bytes from the 1024-aligned base). The 48 KB
-// operand region OPS is reused phase by phase.
-constexpr int P_OPS = 0;
-constexpr int P_A1 = 0;            // phase 1: [beta K alpha ; s Q alpha] bf16 [128][128]  32 KB
-constexpr int P_B1 = 32768;        //          K / alpha                    bf16 [64][128]   16 KB
-constexpr int P_AKK = 0;           // inverse: L fp32 [64][65]
-constexpr int P_AI = 16640;        //          A fp32 [64][65]
-constexpr int P_T = 33280;         //          merge temporaries [3][16][17]
-constexpr int P_BA = 0;            // phase 2: A bf16 [64][64] (B operand, K = j)       8 KB
-constexpr int P_ET = 8192;         //          E^T bf16 [128][64]                      16 KB
-constexpr int P_ZT = 24576;        //          Z^T bf16 [128][64]                      16 KB
-constexpr int P_W = 0;             // output:  W staged bf16 [64][136]
-constexpr int P_ALPHA = 49152;     // alpha = 2^(G2 - c) fp32 [64][129]
-constexpr int P_K = P_ALPHA + 4 * BT * LG;  // keys bf16 [64][128]
-constexpr int P_MISC = P_K + 2 * BT * D;    // beta [64], 2^c [128], 2^(G2_last - c) [128] (floats)
+// Shared-memory map of k_prep_tc (bytes from the 1024-aligned base); regions
+// are reused once the MMA that reads them has completed.
+constexpr int P_A1 = 0;            // [beta K alpha ; s Q alpha] bf16 [128][128], K-major    32 KB
+                                   //   rows 0..63 double as E' (MN-major view) for W^T
+constexpr int P_W = 0;             //   after MMA 2: W staged bf16 [64][LW]
+constexpr int P_B1 = 32768;        // K / alpha bf16 [64][128], K-major                      16 KB
+constexpr int P_LT = 32768;        //   after MMA 1: L^T fp32 [64][64]                        16 KB
+constexpr int P_V = 49152;         // V bf16 [64][128] (MN-major view for U^T)              16 KB
+constexpr int P_ALPHA = 65536;     // G2, then alpha = 2^(G2 - c), fp32 [64][LG]            33 KB
+constexpr int P_BA = 65536;        //   after MMA 1: A bf16 [64][64], K-major                 8 KB
+constexpr int P_BB = 65536 + 8192; //                A diag(beta) bf16 [64][64], K-major      8 KB
+constexpr int P_MISC = P_ALPHA + 4 * BT * LG;  // beta [64], 2^c [128], 2^(G2_last - c) [128]
 constexpr int P_BAR = P_MISC + 4 * (BT + 2 * D);
 constexpr size_t PREP_SMEM = P_BAR + 64 + 1024;
+static_assert(P_BB + 8192 <= P_MISC, "A tiles overlap the constants");
+static_assert(BT * LW * 2 <= P_B1, "W staging overlaps L^T");
 
 template <int GATE, bool BWD>
 __global__ void __launch_bounds__(PT, 2)
@@ -123,13 +109,10 @@ __global__ void __launch_bounds__(PT, 2)
     unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                            ~static_cast<uintptr_t>(1023));
     float* sA = reinterpret_cast<float*>(base + P_ALPHA);  // G2, then alpha
-    bf16* sK = reinterpret_cast<bf16*>(base + P_K);
     float* sBeta = reinterpret_cast<float*>(base + P_MISC);
     float* sC2 = sBeta + BT;   // 2^c
     float* sAL = sC2 + D;      // 2^(G2_last - c)
-    float* sAkk = reinterpret_cast<float*>(base + P_AKK);
-    float* sAi = reinterpret_cast<float*>(base + P_AI);
-    float* sT = reinterpret_cast<float*>(base + P_T);
+    float* sLt = reinterpret_cast<float*>(base + P_LT);
     uint64_t* bar = reinterpret_cast<uint64_t*>(base + P_BAR);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 1);
     const uint32_t sb = tc::smem_u32(base);
@@ -141,6 +124,7 @@ __global__ void __launch_bounds__(PT, 2)
     const int H = s.H;
     const size_t ch = (size_t)c * H + h;
     const float scale = s.scale;
+    const int c8 = (tid & 15) * 8;   // the 8 feature columns of this thread in every row pass
 
     // ---- batched vector loads: k, q, v (bf16, 8 per 16 B), g (fp32, 4 per 16 B)
     constexpr int NU = BT * D / 8 / PT;   // 16-byte bf16 chunks per thread
@@ -148,7 +132,7 @@ __global__ void __launch_bounds__(PT, 2)
     uint4 kr4[NU], qr4[NU], vr4[NU];
 #pragma unroll
     for (int u = 0; u < NU; ++u) {
-        const int ci = tid + PT * u, r = ci >> 4, c8 = (ci & 15) * 8;
+        const int r = (tid + PT * u) >> 4;
         kr4[u] = qr4[u] = vr4[u] = make_uint4(0, 0, 0, 0);
         if (r < n) {
             const size_t off = ((size_t)(tok0 + r) * H + h) * D + c8;
@@ -174,18 +158,11 @@ __global__ void __launch_bounds__(PT, 2)
 #pragma unroll
         for (int u = 0; u < NG; ++u) {
             const int ci = tid + PT * u, r = ci >> 5, c4 = (ci & 31) * 4;
-            sA[r * LG + c4] = gr4[u].x * LOG2E;
-            sA[r * LG + c4 + 1] = gr4[u].y * LOG2E;
-            sA[r * LG + c4 + 2] = gr4[u].z * LOG2E;
-            sA[r * LG + c4 + 3] = gr4[u].w * LOG2E;
+            *reinterpret_cast<float4*>(sA + r * LG + c4) =
+                make_float4(gr4[u].x * LOG2E, gr4[u].y * LOG2E, gr4[u].z * LOG2E, gr4[u].w * LOG2E);
         }
     }
     if (tid < BT) sBeta[tid] = (tid < n) ? bfx(beta + (size_t)(tok0 + tid) * H + h) : 0.f;
-#pragma unroll
-    for (int u = 0; u < NU; ++u) {
-        const int ci = tid + PT * u, r = ci >> 4, c8 = (ci & 15) * 8;
-        *reinterpret_cast<uint4*>(sK + r * D + c8) = kr4[u];
-    }
     if (tid == 0) {
         tc::mbar_init(bar, 1);
         tc::fence_mbar_init();
@@ -240,30 +217,44 @@ __global__ void __launch_bounds__(PT, 2)
     if (tid == 0) f.WIDE[ch] = wide ? 1 : 0;
     bool ok = true;
     if (!wide) {
-        // a2 operands (bf16): A rows 0..63 beta_i k_i alpha_i, rows 64..127 s q_i alpha_i; B rows j:
-        // k_j / alpha_j. Q_g = s q alpha 2^c is written from the same registers.
+        // a2 operands (bf16), one pass over the row chunks of this thread: A1 rows 0..63
+        // beta_i k_i alpha_i, rows 64..127 s q_i alpha_i; B1 rows j: k_j / alpha_j; V as loaded.
+        // Q_g = s q alpha 2^c and F = K 2^(G2_last - G2) = k 2^(G2_last - c) / alpha go to HBM.
+        float c2r[8], alr[8];
+#pragma unroll
+        for (int e = 0; e < 8; e += 4) {
+            *reinterpret_cast<float4*>(c2r + e) = *reinterpret_cast<const float4*>(sC2 + c8 + e);
+            *reinterpret_cast<float4*>(alr + e) = *reinterpret_cast<const float4*>(sAL + c8 + e);
+        }
 #pragma unroll
         for (int u = 0; u < NU; ++u) {
-            const int ci = tid + PT * u, i = ci >> 4, c8 = (ci & 15) * 8;
+            const int i = (tid + PT * u) >> 4;
             const bf16* kv = reinterpret_cast<const bf16*>(&kr4[u]);
             const bf16* qv = reinterpret_cast<const bf16*>(&qr4[u]);
-            const float* al = sA + i * LG + c8;
+            float al[8];
+            *reinterpret_cast<float4*>(al) = *reinterpret_cast<const float4*>(sA + i * LG + c8);
+            *reinterpret_cast<float4*>(al + 4) = *reinterpret_cast<const float4*>(sA + i * LG + c8 + 4);
             const float bt = sBeta[i];
-            uint32_t pe[4], pq[4], pz[4], pg[4];
+            uint32_t pe[4], pq[4], pz[4], pg[4], pf[4];
 #pragma unroll
             for (int e = 0; e < 8; e += 2) {
                 const float a0 = al[e], a1 = al[e + 1];
+                const float r0 = tc::rcp_approx(a0), r1 = tc::rcp_approx(a1);
                 const float k0 = __bfloat162float(kv[e]), k1 = __bfloat162float(kv[e + 1]);
-                const float q0 = scale * __bfloat162float(qv[e]), q1 = scale * __bfloat162float(qv[e + 1]);
+                const float q0 = scale * __bfloat162float(qv[e]) * a0, q1 = scale * __bfloat162float(qv[e + 1]) * a1;
+                const float z0 = k0 * r0, z1 = k1 * r1;
                 pe[e / 2] = tc::pack_bf16(bt * k0 * a0, bt * k1 * a1);
-                pq[e / 2] = tc::pack_bf16(q0 * a0, q1 * a1);
-                pz[e / 2] = tc::pack_bf16(k0 * __frcp_rn(a0), k1 * __frcp_rn(a1));
-                pg[e / 2] = tc::pack_bf16(q0 * a0 * sC2[c8 + e], q1 * a1 * sC2[c8 + e + 1]);
+                pq[e / 2] = tc::pack_bf16(q0, q1);
+                pz[e / 2] = tc::pack_bf16(z0, z1);
+                pg[e / 2] = tc::pack_bf16(q0 * c2r[e], q1 * c2r[e + 1]);
+                pf[e / 2] = tc::pack_bf16(z0 * alr[e], z1 * alr[e + 1]);
             }
             *reinterpret_cast<uint4*>(base + P_A1 + tc::sw128_off(2 * BT, i, c8 * 2)) = make_uint4(pe[0], pe[1], pe[2], pe[3]);
             *reinterpret_cast<uint4*>(base + P_A1 + tc::sw128_off(2 * BT, BT + i, c8 * 2)) = make_uint4(pq[0], pq[1], pq[2], pq[3]);
             *reinterpret_cast<uint4*>(base + P_B1 + tc::sw128_off(BT, i, c8 * 2)) = make_uint4(pz[0], pz[1], pz[2], pz[3]);
+            *reinterpret_cast<uint4*>(base + P_V + tc::sw128_off(BT, i, c8 * 2)) = vr4[u];
             *reinterpret_cast<uint4*>(f.QG + ch * BT * D + (size_t)i * D + c8) = make_uint4(pg[0], pg[1], pg[2], pg[3]);
+            *reinterpret_cast<uint4*>(f.KG + ch * BT * D + (size_t)i * D + c8) = make_uint4(pf[0], pf[1], pf[2], pf[3]);
         }
         tc::fence_async_smem();
         __syncthreads();
@@ -275,24 +266,12 @@ __global__ void __launch_bounds__(PT, 2)
                 tc::mma_bf16(tb, tc::sdesc_k(sb + P_A1, 2 * BT, st), tc::sdesc_k(sb + P_B1, BT, st), id, st > 0);
             tc::mma_commit(bar);
         }
-        // F = K 2^(G2_last - G2) = K (2^(G2_last - c)) / alpha, while the MMA runs
-#pragma unroll
-        for (int u = 0; u < NU; ++u) {
-            const int ci = tid + PT * u, i = ci >> 4, c8 = (ci & 15) * 8;
-            const bf16* kv = reinterpret_cast<const bf16*>(&kr4[u]);
-            const float* al = sA + i * LG + c8;
-            uint32_t pk[4];
-#pragma unroll
-            for (int e = 0; e < 8; e += 2)
-                pk[e / 2] = tc::pack_bf16(__bfloat162float(kv[e]) * sAL[c8 + e] * __frcp_rn(al[e]),
-                                          __bfloat162float(kv[e + 1]) * sAL[c8 + e + 1] * __frcp_rn(al[e + 1]));
-            *reinterpret_cast<uint4*>(f.KG + ch * BT * D + (size_t)i * D + c8) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        }
         ok = wait_all(bar, 0, t.err);
     }
     if (!wide && ok) {
         tc::fence_after_sync();
-        // read back [Akk ; Aqk]: warps w and w+4 share lanes 32(w%4).., 32 columns each
+        // read back [Akk ; Aqk]: warps w and w+4 share lanes 32(w%4).., 32 columns each;
+        // Akk -> L^T (fp32, strict, rows < n), Aqk -> C_q (bf16, inclusive) in HBM
         {
             const int row = 32 * (warp & 3) + lane, cb = (warp >> 2) * 32;
             float a[32];
@@ -304,7 +283,7 @@ __global__ void __launch_bounds__(PT, 2)
 #pragma unroll
                 for (int jj = 0; jj < 32; ++jj) {
                     const int j = cb + jj;
-                    sAkk[i * LA + j] = (j < i && i < n) ? a[jj] : 0.f;
+                    sLt[j * BT + i] = (j < i && i < n) ? a[jj] : 0.f;
                 }
             } else {
                 const int i = row - BT;
@@ -319,72 +298,64 @@ __global__ void __launch_bounds__(PT, 2)
                 for (int qq = 0; qq < 4; ++qq) dst[qq] = make_uint4(pw[4 * qq], pw[4 * qq + 1], pw[4 * qq + 2], pw[4 * qq + 3]);
             }
         }
-        tc::fence_before_sync();
         __syncthreads();
-        // a3: A = (I + Akk)^-1
-        blocked_inverse(sAkk, sAi, sT, tid);
-        // a4: A as the bf16 B operand of W^T = E^T A^T (rows i, K = j); A for the backward
-        for (int idx = tid; idx < BT * 8; idx += PT) {
-            const int i = idx >> 3, j8 = (idx & 7) * 8;
-            const float* ai = sAi + i * LA + j8;
-            uint32_t pw[4];
+        // a3 + a4: A = (I + Akk)^-1 in registers, then the bf16 B operands A (for W^T = E'^T A^T)
+        // and A diag(beta) (for U^T = V^T (A diag(beta))^T), and A itself for the backward
+        {
+            float x0[8], x1[8];
+            inverse_rows(sLt, warp, lane, x0, x1);
+            const int cb = 8 * warp;
+            float bj[8];
+            *reinterpret_cast<float4*>(bj) = *reinterpret_cast<const float4*>(sBeta + cb);
+            *reinterpret_cast<float4*>(bj + 4) = *reinterpret_cast<const float4*>(sBeta + cb + 4);
+            uint32_t a0[4], a1[4], b0[4], b1[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) pw[e] = tc::pack_bf16(ai[2 * e], ai[2 * e + 1]);
-            const uint4 val = make_uint4(pw[0], pw[1], pw[2], pw[3]);
-            *reinterpret_cast<uint4*>(base + P_BA + tc::sw128_off(BT, i, j8 * 2)) = val;
-            if (BWD) *reinterpret_cast<uint4*>(f.AI + ch * BT * BT + (size_t)i * BT + j8) = val;
-        }
-        __syncthreads();  // A (fp32) consumed: E^T and Z^T may overwrite it
-        // E^T [128 keys][64 tokens] = beta k 2^G2 = beta k alpha 2^c ; Z^T [128 values][64 tokens] = beta v
-        for (int idx = tid; idx < D * 8; idx += PT) {
-            const int kr = idx & (D - 1), j8 = (idx >> 7) * 8;
-            const float c2 = sC2[kr];
-            uint32_t pw[4];
-#pragma unroll
-            for (int e = 0; e < 8; e += 2) {
-                const int j = j8 + e;
-                pw[e / 2] = tc::pack_bf16(sBeta[j] * __bfloat162float(sK[j * D + kr]) * sA[j * LG + kr] * c2,
-                                          sBeta[j + 1] * __bfloat162float(sK[(j + 1) * D + kr]) * sA[(j + 1) * LG + kr] * c2);
+            for (int e = 0; e < 4; ++e) {
+                a0[e] = tc::pack_bf16(x0[2 * e], x0[2 * e + 1]);
+                a1[e] = tc::pack_bf16(x1[2 * e], x1[2 * e + 1]);
+                b0[e] = tc::pack_bf16(x0[2 * e] * bj[2 * e], x0[2 * e + 1] * bj[2 * e + 1]);
+                b1[e] = tc::pack_bf16(x1[2 * e] * bj[2 * e], x1[2 * e + 1] * bj[2 * e + 1]);
             }
-            *reinterpret_cast<uint4*>(base + P_ET + tc::sw128_off(D, kr, j8 * 2)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
-        }
-#pragma unroll
-        for (int u = 0; u < NU; ++u) {
-            const int ci = tid + PT * u, j = ci >> 4, c8 = (ci & 15) * 8;
-            const bf16* pv = reinterpret_cast<const bf16*>(&vr4[u]);
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                *reinterpret_cast<bf16*>(base + P_ZT + tc::sw128_off(D, c8 + e, j * 2)) =
-                    __float2bfloat16_rn(sBeta[j] * __bfloat162float(pv[e]));
+            const uint4 va0 = make_uint4(a0[0], a0[1], a0[2], a0[3]), va1 = make_uint4(a1[0], a1[1], a1[2], a1[3]);
+            *reinterpret_cast<uint4*>(base + P_BA + tc::sw128_off(BT, lane, 2 * cb)) = va0;
+            *reinterpret_cast<uint4*>(base + P_BA + tc::sw128_off(BT, lane + 32, 2 * cb)) = va1;
+            *reinterpret_cast<uint4*>(base + P_BB + tc::sw128_off(BT, lane, 2 * cb)) = make_uint4(b0[0], b0[1], b0[2], b0[3]);
+            *reinterpret_cast<uint4*>(base + P_BB + tc::sw128_off(BT, lane + 32, 2 * cb)) = make_uint4(b1[0], b1[1], b1[2], b1[3]);
+            if (BWD) {
+                *reinterpret_cast<uint4*>(f.AI + ch * BT * BT + (size_t)lane * BT + cb) = va0;
+                *reinterpret_cast<uint4*>(f.AI + ch * BT * BT + (size_t)(lane + 32) * BT + cb) = va1;
+            }
         }
         tc::fence_async_smem();
         tc::fence_before_sync();
         __syncthreads();
         if (tid == 0) {
             tc::fence_after_sync();
-            const uint32_t id = tc::idesc_bf16(128, 64);
+            // W^T 2^-c = E'^T A^T and U^T = V^T (A diag(beta))^T; E' and V are read MN-major
+            const uint32_t id = tc::idesc_bf16_amn(128, 64);
 #pragma unroll 1
             for (int st = 0; st < 4; ++st)
-                tc::mma_bf16(tb + 64, tc::sdesc_k(sb + P_ET, D, st), tc::sdesc_k(sb + P_BA, BT, st), id, st > 0);
+                tc::mma_bf16(tb + 64, tc::sdesc_mn(sb + P_A1, 2 * BT * 128, st), tc::sdesc_k(sb + P_BA, BT, st), id, st > 0);
 #pragma unroll 1
             for (int st = 0; st < 4; ++st)
-                tc::mma_bf16(tb + 128, tc::sdesc_k(sb + P_ZT, D, st), tc::sdesc_k(sb + P_BA, BT, st), id, st > 0);
+                tc::mma_bf16(tb + 128, tc::sdesc_mn(sb + P_V, BT * 128, st), tc::sdesc_k(sb + P_BB, BT, st), id, st > 0);
             tc::mma_commit(bar);
         }
         ok = wait_all(bar, 1, t.err);
         if (ok) {
             tc::fence_after_sync();
-            bf16* sW = reinterpret_cast<bf16*>(base + P_W);   // staged W [64][136]
+            bf16* sW = reinterpret_cast<bf16*>(base + P_W);   // staged W [64][LW]
             const int row = 32 * (warp & 3) + lane;
             if (warp < 4) {
-                // W^T row = key `row` -> staged W[i][row]
+                // W^T row = key `row`, scaled by 2^c -> staged W[i][row]
+                const float c2 = sC2[row];
 #pragma unroll
                 for (int cb = 0; cb < BT; cb += 16) {
                     float a[16];
                     tc::tmem_ld16(tc::taddr(tb + 64, 32 * warp, cb), a);
                     tc::tmem_wait_ld();
 #pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) sW[(cb + jj) * LW + row] = __float2bfloat16_rn(a[jj]);
+                    for (int jj = 0; jj < 16; ++jj) sW[(cb + jj) * LW + row] = __float2bfloat16_rn(a[jj] * c2);
                 }
             } else {
                 // U^T row = value `row` -> U[i][row] (fp32, coalesced over the value index)
@@ -400,8 +371,8 @@ __global__ void __launch_bounds__(PT, 2)
             }
             __syncthreads();
             for (int idx = tid; idx < BT * 16; idx += PT) {
-                const int i = idx >> 4, c8 = (idx & 15) * 8;
-                *reinterpret_cast<uint4*>(f.W + ch * BT * D + (size_t)i * D + c8) = *reinterpret_cast<const uint4*>(sW + i * LW + c8);
+                const int i = idx >> 4, cc8 = (idx & 15) * 8;
+                *reinterpret_cast<uint4*>(f.W + ch * BT * D + (size_t)i * D + cc8) = *reinterpret_cast<const uint4*>(sW + i * LW + cc8);
             }
         }
     }

@@ -70,6 +70,8 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
 }
 // bf16, K-major A, MN-major B.
 __host__ __device__ constexpr uint32_t idesc_bf16_bmn(int M, int N) { return idesc_bf16(M, N) | (1u << 16); }
+// bf16, MN-major A, K-major B.
+__host__ __device__ constexpr uint32_t idesc_bf16_amn(int M, int N) { return idesc_bf16(M, N) | (1u << 15); }
 __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
     return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
@@ -230,6 +232,14 @@ __device__ __forceinline__ void warp_store_t16(__nv_bfloat16* stg, const float (
 }
 
 // bf16 pair packing
+// Approximate reciprocal (the PTX rcp.approx instruction, about 1 ulp); for
+// operands that are rounded to bf16 afterwards.
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 t = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&t);
