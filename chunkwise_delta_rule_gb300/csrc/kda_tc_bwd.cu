@@ -13,7 +13,7 @@
 // go to HBM (bf16) for the consumer. C_q, A, Q_g and W are read as MN-major
 // operands from their natural [token][.] layouts.
 //
-// k_bwd_consumer_tc (a9-a12), one CTA per (chunk slot, head), 256 threads:
+// k_bwd_consumer_tc (a9-a12), one CTA per (chunk slot, head), 512 threads:
 //     [H_q ; -D] = [dO ; P] R^T   (masked: inclusive / strict, sign of D)
 //     [dO S^T ; P S^T] = [dO ; P] S^T        F_bar^T = S+bar R^T
 //     [T_q ; T_e] = [H_q ; D] (K zeta)        (A operand read from TMEM)
@@ -44,15 +44,18 @@ __device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, int32_t
     return ok;
 }
 
-// Copies a row-major bf16 [R][C] global tile (row stride `ld` elements) into a
-// K-major SW128 smem tile; rows >= valid are zero-filled.
-template <int R, int C, int NT>
-__device__ __forceinline__ void load_tile(uint32_t sbase, const bf16* src, size_t ld, int valid, int tid) {
+// Copies a row-major bf16 [R][C] global tile (row stride `ld` elements) into
+// rows row0.. of a K-major SW128 smem tile of RT rows; rows >= valid are
+// zero-filled.
+template <int R, int C, int NT, int RT = R>
+__device__ __forceinline__ void load_tile(uint32_t sbase, const bf16* src, size_t ld, int valid, int tid,
+                                          int row0 = 0) {
     constexpr int CPR = C * 2 / 16;
     for (int idx = tid; idx < R * CPR; idx += NT) {
         const int r = idx / CPR, cc = idx % CPR;
         const bool in = r < valid;
-        tc::cp_async16(sbase + tc::sw128_off(R, r, cc * 16), src + (in ? (size_t)r * ld + cc * 8 : 0), in ? 16u : 0u);
+        tc::cp_async16(sbase + tc::sw128_off(RT, row0 + r, cc * 16), src + (in ? (size_t)r * ld + cc * 8 : 0),
+                       in ? 16u : 0u);
     }
 }
 
@@ -278,16 +281,15 @@ constexpr int CT = 512;   // 16 warps: four warps share each TMEM lane quarter a
 constexpr int LG = D + 1;
 // region X (128 KB): phase A operands, then phase B operands, then final tiles
 constexpr int X_OP = 0;          // [dO ; P]   bf16 [128][128]   32 KB
-constexpr int X_R = 32768;       // R          bf16 [64][128]    16 KB
-constexpr int X_S = 49152;       // S          bf16 [128][128]   32 KB
+constexpr int X_RS = 32768;      // [R ; S]    bf16 [192][128]   48 KB
 constexpr int X_SB = 81920;      // S+bar      bf16 [128][128]   32 KB
 constexpr int X_EQ = 0;          // [E_a^T | Q_a^T] tf32 [128][128] 64 KB
 constexpr int X_KZ = 65536;      // (K zeta)^T tf32 [128][64]    32 KB
 constexpr int X_DH = 98304;      // [D ; H_q]^T tf32 [64][128]   32 KB
 constexpr int X_BYTES = 131072;
 constexpr int C_A = X_BYTES;                      // G2, then alpha = 2^(G2 - c), fp32 [64][129]
-constexpr int C_K = C_A + 4 * BT * LG;            // k bf16 [64][128]
-constexpr int C_Q = C_K + 2 * BT * D;             // q bf16 [64][128]
+constexpr int C_K = C_A + 4 * BT * LG;            // k bf16 [64][128], SW128 rows (conflict-free row and column reads)
+constexpr int C_Q = C_K + 2 * BT * D;             // q bf16 [64][128], SW128 rows
 constexpr int C_MISC = C_Q + 2 * BT * D;          // small arrays (floats)
 constexpr int M_BETA = 0, M_C2 = 64, M_AL = 192, M_LAMB = 320, M_DBW = 448, M_ROWP = 512,
               M_ENDP = 768, M_ROW = 1280, M_END = 1344;
@@ -295,6 +297,11 @@ constexpr int C_BAR = C_MISC + 4 * M_END;
 constexpr int CONS_SMEM = C_BAR + 64 + 1024;
 
 __device__ __forceinline__ float bfx(const bf16* p) { return __bfloat162float(*p); }
+
+// Element (r, col) of a [64][128] bf16 tile stored in SW128 rows.
+__device__ __forceinline__ float ldsw(const unsigned char* tile, int r, int col) {
+    return __bfloat162float(*reinterpret_cast<const bf16*>(tile + tc::sw128_off(BT, r, col * 2)));
+}
 
 template <int GATE>
 __global__ void __launch_bounds__(CT, 1)
@@ -307,8 +314,8 @@ __global__ void __launch_bounds__(CT, 1)
     unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                            ~static_cast<uintptr_t>(1023));
     float* sA = reinterpret_cast<float*>(base + C_A);
-    bf16* sK = reinterpret_cast<bf16*>(base + C_K);
-    bf16* sQ = reinterpret_cast<bf16*>(base + C_Q);
+    const unsigned char* sK = base + C_K;
+    const unsigned char* sQ = base + C_Q;
     float* sm = reinterpret_cast<float*>(base + C_MISC);
     float* sBeta = sm + M_BETA;
     float* sC2 = sm + M_C2;       // 2^c per feature
@@ -352,23 +359,26 @@ __global__ void __launch_bounds__(CT, 1)
             const bf16* src = isO ? dO0 + (in ? (size_t)r * rowstride + cc * 8 : 0) : P0 + (size_t)(r - BT) * D + cc * 8;
             tc::cp_async16(sb + X_OP + tc::sw128_off(2 * BT, r, cc * 16), src, in ? 16u : 0u);
         }
-        load_tile<BT, D, CT>(sb + X_R, f.R + ch * BT * D, D, BT, tid);
-        load_tile<D, D, CT>(sb + X_S, f.HS + ch * D * D, D, D, tid);
+        load_tile<BT, D, CT, BT + D>(sb + X_RS, f.R + ch * BT * D, D, BT, tid, 0);
+        load_tile<D, D, CT, BT + D>(sb + X_RS, f.HS + ch * D * D, D, D, tid, BT);
         load_tile<D, D, CT>(sb + X_SB, b.SBP + ch * D * D, D, D, tid);
         tc::cp_async_commit();
     }
-    // raw inputs: k, q (bf16 rows), g (log2 units), beta
+    // raw inputs: k, q (bf16 rows), g (log2 units), beta; v stays in registers for dv
+    constexpr int NU = BT * D / 8 / CT;
+    uint4 vr4[NU];
     {
-        constexpr int NU = BT * D / 8 / CT, NG = BT * D / 4 / CT;
+        constexpr int NG = BT * D / 4 / CT;
         uint4 kr4[NU], qr4[NU];
 #pragma unroll
         for (int u = 0; u < NU; ++u) {
             const int ci = tid + CT * u, r = ci >> 4, c8 = (ci & 15) * 8;
-            kr4[u] = qr4[u] = make_uint4(0, 0, 0, 0);
+            kr4[u] = qr4[u] = vr4[u] = make_uint4(0, 0, 0, 0);
             if (r < n) {
                 const size_t off = ((size_t)(tok0 + r) * H + h) * D + c8;
                 kr4[u] = __ldg(reinterpret_cast<const uint4*>(k + off));
                 qr4[u] = __ldg(reinterpret_cast<const uint4*>(q + off));
+                vr4[u] = __ldg(reinterpret_cast<const uint4*>(v + off));
             }
         }
         float4 gr4[NG];
@@ -387,8 +397,8 @@ __global__ void __launch_bounds__(CT, 1)
 #pragma unroll
         for (int u = 0; u < NU; ++u) {
             const int ci = tid + CT * u, r = ci >> 4, c8 = (ci & 15) * 8;
-            *reinterpret_cast<uint4*>(sK + r * D + c8) = kr4[u];
-            *reinterpret_cast<uint4*>(sQ + r * D + c8) = qr4[u];
+            *reinterpret_cast<uint4*>(base + C_K + tc::sw128_off(BT, r, c8 * 2)) = kr4[u];
+            *reinterpret_cast<uint4*>(base + C_Q + tc::sw128_off(BT, r, c8 * 2)) = qr4[u];
         }
 #pragma unroll
         for (int u = 0; u < NG; ++u) {
@@ -409,16 +419,14 @@ __global__ void __launch_bounds__(CT, 1)
     // TMEM columns: [0,64) [H_q ; -D] -> [H_q ; D] ; [64,192) [dO S^T ; P S^T] ;
     // [192,256) F_bar^T ; [256,384) [T_q ; T_e] ; [384,448) T_y^T
     if (tid == 0) {
-        const uint32_t i64 = tc::idesc_bf16(128, 64), i128 = tc::idesc_bf16(128, 128);
+        // [dO ; P] [R ; S]^T fills columns [0, 192) in one N = 192 pass
+        const uint32_t i64 = tc::idesc_bf16(128, 64), i192 = tc::idesc_bf16(128, BT + D);
 #pragma unroll 1
         for (int ks = 0; ks < 8; ++ks)
-            tc::mma_bf16(tb, tc::sdesc_k(sb + X_OP, D, ks), tc::sdesc_k(sb + X_R, BT, ks), i64, ks > 0);
+            tc::mma_bf16(tb, tc::sdesc_k(sb + X_OP, D, ks), tc::sdesc_k(sb + X_RS, BT + D, ks), i192, ks > 0);
 #pragma unroll 1
         for (int ks = 0; ks < 8; ++ks)
-            tc::mma_bf16(tb + 64, tc::sdesc_k(sb + X_OP, D, ks), tc::sdesc_k(sb + X_S, D, ks), i128, ks > 0);
-#pragma unroll 1
-        for (int ks = 0; ks < 8; ++ks)
-            tc::mma_bf16(tb + 192, tc::sdesc_k(sb + X_SB, D, ks), tc::sdesc_k(sb + X_R, BT, ks), i64, ks > 0);
+            tc::mma_bf16(tb + 192, tc::sdesc_k(sb + X_SB, D, ks), tc::sdesc_k(sb + X_RS, BT + D, ks), i64, ks > 0);
         tc::mma_commit(bar);
     }
     // while the MMAs run: cumsum (4 segments of 16 rows per feature), anchors, alpha tile;
@@ -464,9 +472,8 @@ __global__ void __launch_bounds__(CT, 1)
         float acc = 0.f;
 #pragma unroll 4
         for (int cc = 0; cc < 16; ++cc) {
-            const uint32_t o = tc::sw128_off(D, kr, cc * 16);
-            const uint4 a = *reinterpret_cast<const uint4*>(base + X_S + o);
-            const uint4 bb = *reinterpret_cast<const uint4*>(base + X_SB + o);
+            const uint4 a = *reinterpret_cast<const uint4*>(base + X_RS + tc::sw128_off(BT + D, BT + kr, cc * 16));
+            const uint4 bb = *reinterpret_cast<const uint4*>(base + X_SB + tc::sw128_off(D, kr, cc * 16));
             const bf16* pa = reinterpret_cast<const bf16*>(&a);
             const bf16* pb = reinterpret_cast<const bf16*>(&bb);
 #pragma unroll
@@ -474,14 +481,16 @@ __global__ void __launch_bounds__(CT, 1)
         }
         sLamb[kr] = acc;
     }
-    for (int idx = tid; idx < BT * 16; idx += CT) {   // 16 threads per row, 8 values each
-        const int r = idx >> 4, cc = idx & 15;
+    static_assert(NU * CT == BT * 16, "dv pass follows the v load map");
+#pragma unroll
+    for (int u = 0; u < NU; ++u) {   // 16 threads per row, 8 values each (the v load map)
+        const int idx = tid + CT * u, r = idx >> 4, cc = idx & 15;
         float acc = 0.f;
         if (r < n) {
             const size_t tok = (size_t)(tok0 + r) * H + h;
-            const float bt = bfx(beta + tok);
+            const float bt = sBeta[r];
             const uint4 pp = *reinterpret_cast<const uint4*>(base + X_OP + tc::sw128_off(2 * BT, BT + r, cc * 16));
-            const uint4 vv = __ldg(reinterpret_cast<const uint4*>(v + tok * D + cc * 8));
+            const uint4 vv = vr4[u];
             const bf16* pp2 = reinterpret_cast<const bf16*>(&pp);
             const bf16* vv2 = reinterpret_cast<const bf16*>(&vv);
             uint32_t out[4];
@@ -517,7 +526,7 @@ __global__ void __launch_bounds__(CT, 1)
             for (int jj = 0; jj < 16; ++jj) {
                 const int j = cb0 + jj;
                 float x = (i < n && (isH ? j <= i : j < i)) ? (isH ? a[jj] : -a[jj]) : 0.f;
-                if (GATE == 1) x *= fminf(ai * __frcp_rn(sA[j * LG]), 1.f);
+                if (GATE == 1) x *= fminf(ai * tc::rcp_approx(sA[j * LG]), 1.f);
                 a[jj] = x;
                 const int kidx = isH ? BT + i : i;   // K order of T_y^T: D rows first, then H_q rows
                 *reinterpret_cast<float*>(base + X_DH + tc::sw128_off(BT, j, kidx * 4)) = x;
@@ -533,8 +542,8 @@ __global__ void __launch_bounds__(CT, 1)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int j = 4 * cc + e;
-                const float kv = __bfloat162float(sK[j * D + kr]);
-                pv[e] = (GATE == 2) ? kv * __frcp_rn(sA[j * LG + kr]) : kv;
+                const float kv = ldsw(sK, j, kr);
+                pv[e] = (GATE == 2) ? kv * tc::rcp_approx(sA[j * LG + kr]) : kv;
             }
             *reinterpret_cast<float4*>(base + X_KZ + tc::sw128_off(D, kr, cc * 16)) = val;
         }
@@ -548,8 +557,7 @@ __global__ void __launch_bounds__(CT, 1)
                 const int kk = 4 * cc + e;
                 const int j = kk & (BT - 1);
                 const float al = (GATE == 2) ? sA[j * LG + kr] : 1.f;
-                pv[e] = (kk < BT) ? sBeta[j] * __bfloat162float(sK[j * D + kr]) * al
-                                  : scale * __bfloat162float(sQ[j * D + kr]) * al;
+                pv[e] = (kk < BT) ? sBeta[j] * ldsw(sK, j, kr) * al : scale * ldsw(sQ, j, kr) * al;
             }
             *reinterpret_cast<float4*>(base + X_EQ + tc::sw128_off(D, kr, cc * 16)) = val;
         }
@@ -582,6 +590,15 @@ __global__ void __launch_bounds__(CT, 1)
             const float bt = sBeta[i];
             float part = 0.f;
             uint32_t packed[16];
+            // q_i (query rows) or k_i (key rows), columns cb0..cb0+31: four 16-byte chunks
+            uint4 xr4[4];
+            {
+                const unsigned char* src = isQ ? sQ : sK;
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq)
+                    xr4[qq] = *reinterpret_cast<const uint4*>(src + tc::sw128_off(BT, i, (cb0 + 8 * qq) * 2));
+            }
+            const bf16* xv = reinterpret_cast<const bf16*>(xr4);
 #pragma unroll
             for (int cb = 0; cb < 32; cb += 16) {
                 float tq[16], tp[16];
@@ -594,13 +611,14 @@ __global__ void __launch_bounds__(CT, 1)
                     const float al = sA[i * LG + kr];
                     const float fac = (GATE == 2) ? al : 1.f;      // alpha (unit: folded / no gate)
                     const float gam = al * sC2[kr];                 // gamma = 2^G2
+                    const float xq = __bfloat162float(xv[cb + jj]);
                     if (isQ) {
                         const float Qt = fac * tq[jj] + gam * tp[jj];               // gamma * Q_g_bar
-                        sGQ[i * LG + kr] = scale * __bfloat162float(sQ[i * D + kr]) * Qt;
+                        sGQ[i * LG + kr] = scale * xq * Qt;
                         tq[jj] = scale * Qt;
                     } else {
                         const float Et = fac * tq[jj] - gam * tp[jj];               // gamma * E_bar
-                        const float kv = __bfloat162float(sK[i * D + kr]);
+                        const float kv = xq;
                         sDK[i * LG + kr] = bt * Et;
                         sGE[i * LG + kr] = bt * kv * Et;
                         part = fmaf(kv, Et, part);
@@ -635,11 +653,11 @@ __global__ void __launch_bounds__(CT, 1)
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
                 const int j = cb0 + jj;
-                const float rinv = __frcp_rn(sA[j * LG + kr]);
+                const float rinv = tc::rcp_approx(sA[j * LG + kr]);
                 const float ze = (GATE == 2) ? rinv : 1.f;
                 const float dec = al_last * rinv;                   // lambda / gamma_j
                 const float Yt = ze * ty[jj] + fb[jj] * dec;        // Y_bar / gamma
-                const float kv = __bfloat162float(sK[j * D + kr]);
+                const float kv = ldsw(sK, j, kr);
                 sDK[j * LG + kr] += Yt;
                 sGQ[j * LG + kr] -= kv * Yt;
                 if (j < n) endp = fmaf(kv * dec, fb[jj], endp);      // F_j . F_bar_j
