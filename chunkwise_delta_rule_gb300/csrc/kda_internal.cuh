@@ -19,6 +19,15 @@ constexpr float CENTER_RANGE_LOG2 = 80.0f;
 constexpr float LOG2E = 1.4426950408889634f;
 
 // Chunk bookkeeping built on the device from cu_seqlens (or from B, T).
+// The bf16 tensor-core intermediates (W, F, Q_g, C_q, A) are stored in HBM as
+// images of their shared-memory operand tiles: a [R][C] tile (C = 64 or 128)
+// in the K-major 128-byte swizzle layout (64-column atom blocks of R rows of
+// 128 bytes; the 16-byte chunk c of row r sits at position c ^ (r % 8)), so a
+// single bulk copy stages a whole tile. Element offset of (r, col):
+__host__ __device__ __forceinline__ int tile_el(int R, int r, int col) {
+    return ((col >> 6) * R + r) * 64 + ((((col >> 3) & 7) ^ (r & 7)) << 3) + (col & 7);
+}
+
 struct Table {
     int32_t* chunk_tok0;  // [NC] first token of the chunk (packed axis)
     int32_t* chunk_len;   // [NC] tokens in the chunk; 0 marks an unused slot

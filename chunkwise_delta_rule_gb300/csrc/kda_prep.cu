@@ -18,7 +18,7 @@ namespace kda {
 namespace {
 
 // TCOUT: prepare only the chunks the tensor-core prep flagged as too wide for
-// one anchor, and write the tensor-core path's layouts (bf16 tiles).
+// one anchor, and write the tensor-core path's layouts (bf16 tile images).
 template <typename TI, int D, int GATE, bool TCOUT>
 __global__ void __launch_bounds__(NTHREADS, 1)
     k_prep(Shape s, const TI* __restrict__ q, const TI* __restrict__ k, const TI* __restrict__ v,
@@ -104,7 +104,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 } else {
                     const float x = (j <= i && i < n) ? acc[ii][jj] : 0.f;
                     if (TCOUT) {
-                        ft.AQK[ch * BT * BT + i * BT + j] = __float2bfloat16_rn(x);
+                        ft.AQK[ch * BT * BT + tile_el(BT, i, j)] = __float2bfloat16_rn(x);
                     } else {
                         AQK[i * BT + j] = x;
                     }
@@ -141,8 +141,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const float qg = scale * sQ[r * LD + col] * exp2f(gr);
             const float kg = sK[r * LD + col] * exp2f(gl[col] - gr);
             if (TCOUT) {
-                ft.QG[ch * BT * D + idx] = __float2bfloat16_rn(qg);
-                ft.KG[ch * BT * D + idx] = __float2bfloat16_rn(kg);
+                ft.QG[ch * BT * D + tile_el(BT, r, col)] = __float2bfloat16_rn(qg);
+                ft.KG[ch * BT * D + tile_el(BT, r, col)] = __float2bfloat16_rn(kg);
             } else {
                 f.QG[ch * BT * D + idx] = qg;
                 f.KG[ch * BT * D + idx] = kg;
@@ -152,7 +152,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int idx = tid; idx < BT * BT; idx += NTHREADS) {
             const float a = sAi[(idx / BT) * LA + idx % BT];
             if (TCOUT) {
-                if (ft.AI) ft.AI[ch * BT * BT + idx] = __float2bfloat16_rn(a);
+                if (ft.AI) ft.AI[ch * BT * BT + tile_el(BT, idx / BT, idx % BT)] = __float2bfloat16_rn(a);
             } else {
                 f.AINV[ch * BT * BT + idx] = a;
             }
@@ -182,7 +182,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             for (int jj = 0; jj < TN; ++jj) {
                 const int r = TM8::row(ii), cl = TM8::col(jj);
                 if (TCOUT) {
-                    ft.W[ch * BT * D + r * D + cl] = __float2bfloat16_rn(acc[ii][jj]);
+                    ft.W[ch * BT * D + tile_el(BT, r, cl)] = __float2bfloat16_rn(acc[ii][jj]);
                 } else {
                     f.W[ch * BT * D + r * D + cl] = acc[ii][jj];
                 }

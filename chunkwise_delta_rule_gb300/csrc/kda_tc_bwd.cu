@@ -1,7 +1,7 @@
 // Tensor-core backward path (bf16 I/O, K = V = 128) on tcgen05.
 //
-// k_bwd_scan_tc (a8, a9 first product), one CTA per (sequence, head), 128
-// threads, thread v owns value column v. The transposed state adjoint
+// k_bwd_scan_tc (a8, a9 first product), one CTA per (sequence, head), 256
+// threads, warps w and w+4 own value columns 32(w%4).. . The transposed state adjoint
 // S_bar^T (V x K, fp32) stays in TMEM; chunks are visited last to first:
 //     R_bar^T = S+bar^T F^T + dO^T C_q          ("State and gate composition":
 //                                               both uses of R before the pullback)
@@ -11,7 +11,7 @@
 // ("ReWY: Faster Backpropagation for Delta-Rule Attention", Algorithm 1 step 5
 // and "Complete Reverse Execution and Boundaries"). S+bar and P of every chunk
 // go to HBM (bf16) for the consumer. C_q, A, Q_g and W are read as MN-major
-// operands from their natural [token][.] layouts.
+// operands from their tile images, staged by bulk copies.
 //
 // k_bwd_consumer_tc (a9-a12), one CTA per (chunk slot, head), 512 threads:
 //     [H_q ; -D] = [dO ; P] R^T   (masked: inclusive / strict, sign of D)
@@ -78,13 +78,16 @@ constexpr int B_TST = B_LAM + 512;             // per-warp transpose staging, 8 
 constexpr int B_BAR = B_TST + 8 * 1280;
 constexpr int BSCAN_SMEM = B_BAR + 64 + 1024;
 
-__device__ __forceinline__ void bscan_prefetch(uint32_t stg, const FwdTC& f, size_t ch, int tid) {
-    load_tile<BT, D, ST>(stg + S_KG, f.KG + ch * BT * D, D, BT, tid);
-    load_tile<BT, BT, ST>(stg + S_AQ, f.AQK + ch * BT * BT, BT, BT, tid);
-    load_tile<BT, BT, ST>(stg + S_AI, f.AI + ch * BT * BT, BT, BT, tid);
-    load_tile<BT, D, ST>(stg + S_QG, f.QG + ch * BT * D, D, BT, tid);
-    load_tile<BT, D, ST>(stg + S_W, f.W + ch * BT * D, D, BT, tid);
-    tc::cp_async_commit();
+// Stages the operand tiles of one chunk (stored as tile images) with bulk
+// copies; one thread; completion arrives on `full` as transaction bytes.
+__device__ __forceinline__ void bscan_fill(uint32_t stg, const FwdTC& f, size_t ch, uint64_t* full) {
+    constexpr uint32_t TILE = BT * D * 2, TQ = BT * BT * 2;
+    tc::mbar_arrive_expect_tx(full, 3 * TILE + 2 * TQ);
+    tc::bulk_g2s(stg + S_KG, f.KG + ch * BT * D, TILE, full);
+    tc::bulk_g2s(stg + S_AQ, f.AQK + ch * BT * BT, TQ, full);
+    tc::bulk_g2s(stg + S_AI, f.AI + ch * BT * BT, TQ, full);
+    tc::bulk_g2s(stg + S_QG, f.QG + ch * BT * D, TILE, full);
+    tc::bulk_g2s(stg + S_W, f.W + ch * BT * D, TILE, full);
 }
 
 __global__ void __launch_bounds__(ST, 1)
@@ -94,8 +97,9 @@ __global__ void __launch_bounds__(ST, 1)
     unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                            ~static_cast<uintptr_t>(1023));
     float* sLam = reinterpret_cast<float*>(base + B_LAM);
-    uint64_t* bar = reinterpret_cast<uint64_t*>(base + B_BAR);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 3);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(base + B_BAR);   // three MMA groups
+    uint64_t* full = bar + 3;                                      // operand stages 0, 1
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 5);
     const uint32_t sb = tc::smem_u32(base);
     const int nseq = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = warp & 3, half = warp >> 2;
@@ -106,16 +110,15 @@ __global__ void __launch_bounds__(ST, 1)
     const int c0 = t.seq_chunk0[nseq], c1 = t.seq_chunk0[nseq + 1];
 
     if (tid == 0) {
-        tc::mbar_init(&bar[0], 1);
-        tc::mbar_init(&bar[1], 1);
-        tc::mbar_init(&bar[2], 1);
+        for (int i = 0; i < 5; ++i) tc::mbar_init(&bar[i], 1);
         tc::fence_mbar_init();
+        if (c0 < c1) bscan_fill(sb + B_STAGE, f, (size_t)(c1 - 1) * H + h, &full[0]);
     }
+    int filled = c0 < c1 ? 1 : 0, waited = 0;   // bulk fills issued / consumed (thread 0)
     if (warp == 0) {
         tc::tmem_alloc(tslot, 256);
         tc::tmem_relinquish();
     }
-    if (c0 < c1) bscan_prefetch(sb + B_STAGE, f, (size_t)(c1 - 1) * H + h, tid);
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
@@ -180,12 +183,13 @@ __global__ void __launch_bounds__(ST, 1)
             tc::tmem_st16(tl + cb, a);
         }
         tc::tmem_wait_st();
-        tc::cp_async_wait_all();
         tc::fence_async_smem();
         tc::fence_before_sync();
         __syncthreads();
         if (tid == 0) {
             tc::fence_after_sync();
+            if (!tc::mbar_wait(&full[stage], (it >> 1) & 1)) atomicOr(t.err, 2);
+            ++waited;
             const uint32_t i64 = tc::idesc_bf16(128, 64);
             const uint32_t m64 = tc::idesc_bf16_bmn(128, 64), m128 = tc::idesc_bf16_bmn(128, 128);
 #pragma unroll 1
@@ -199,7 +203,10 @@ __global__ void __launch_bounds__(ST, 1)
             for (int ks = 0; ks < 4; ++ks)
                 tc::mma_bf16(tb, tc::sdesc_k(sb + B_ADO, D, ks), tc::sdesc_mn(stg + S_QG, BT * 128, ks), m128, 1);
         }
-        if (c - 1 >= c0) bscan_prefetch(sb + B_STAGE + (stage ^ 1) * B_STG, f, (size_t)(c - 1) * H + h, tid);
+        if (c - 1 >= c0 && tid == 0) {
+            bscan_fill(sb + B_STAGE + (stage ^ 1) * B_STG, f, (size_t)(c - 1) * H + h, &full[stage ^ 1]);
+            ++filled;
+        }
         ok = wait_all(&bar[0], ph0, t.err);
         ph0 ^= 1;
         if (!ok) break;
@@ -270,7 +277,9 @@ __global__ void __launch_bounds__(ST, 1)
             for (int jj = 0; jj < 16; ++jj) dh0[st_off + (size_t)(cb + jj) * D + vcol] = a[jj];
         }
     }
-    tc::cp_async_wait_all();
+    // after an early exit, let a bulk fill still in flight land before the CTA leaves
+    if (tid == 0)
+        for (; waited < filled; ++waited) tc::mbar_wait(&full[waited & 1], (waited >> 1) & 1);
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tb, 256);

@@ -13,16 +13,18 @@
 //   MN-major. A chunk whose gate range exceeds 2^80 is left to the CUDA-core
 //   prep (flag WIDE), which anchors per 16-token sub-chunk instead.
 //
-// k_fwd_scan_tc, one CTA per (sequence, head), 128 threads, thread v owns
-// value column v (TMEM lane v). The transposed state S^T (V x K, fp32) stays
-// in TMEM for the whole sequence. Per chunk (a5, a6):
+// k_fwd_scan_tc, one CTA per (sequence, head), 256 threads; warps w and w+4
+// own value columns 32(w%4).. (TMEM lanes) and split the other axis. The
+// transposed state S^T (V x K, fp32) stays in TMEM for the whole sequence.
+// Per chunk (a5, a6):
 //       R^T  = U^T - S^T W^T            (MMA, bf16 S^T staged in smem)
-//       O^T  = S^T Q_g^T + R^T C_q^T    (MMAs, output fused)
 //       S^T <- S^T diag(lambda) + R^T F (lambda applied in TMEM, then MMA)
+//       O^T  = S^T Q_g^T + R^T C_q^T    (MMAs issued after the state update,
+//                                        read back during the next chunk)
 // ("ReWY" paper, "The chunk system and conventional WY backward"; "Kimi Delta
-// Attention" blog, section 6.4). Operands of chunk c+1 are prefetched with
-// cp.async while chunk c computes; F is read as an MN-major operand from its
-// natural [token][key] layout.
+// Attention" blog, section 6.4). The operand tiles of chunk c+1 (stored as
+// tile images) are fetched with bulk copies while chunk c computes; F is read
+// as an MN-major operand.
 #include "kda_internal.cuh"
 #include "tc.cuh"
 
@@ -253,8 +255,8 @@ __global__ void __launch_bounds__(PT, 2)
             *reinterpret_cast<uint4*>(base + P_A1 + tc::sw128_off(2 * BT, BT + i, c8 * 2)) = make_uint4(pq[0], pq[1], pq[2], pq[3]);
             *reinterpret_cast<uint4*>(base + P_B1 + tc::sw128_off(BT, i, c8 * 2)) = make_uint4(pz[0], pz[1], pz[2], pz[3]);
             *reinterpret_cast<uint4*>(base + P_V + tc::sw128_off(BT, i, c8 * 2)) = vr4[u];
-            *reinterpret_cast<uint4*>(f.QG + ch * BT * D + (size_t)i * D + c8) = make_uint4(pg[0], pg[1], pg[2], pg[3]);
-            *reinterpret_cast<uint4*>(f.KG + ch * BT * D + (size_t)i * D + c8) = make_uint4(pf[0], pf[1], pf[2], pf[3]);
+            *reinterpret_cast<uint4*>(f.QG + ch * BT * D + tile_el(BT, i, c8)) = make_uint4(pg[0], pg[1], pg[2], pg[3]);
+            *reinterpret_cast<uint4*>(f.KG + ch * BT * D + tile_el(BT, i, c8)) = make_uint4(pf[0], pf[1], pf[2], pf[3]);
         }
         tc::fence_async_smem();
         __syncthreads();
@@ -293,9 +295,11 @@ __global__ void __launch_bounds__(PT, 2)
                     const int j = cb + jj;
                     pw[jj / 2] = tc::pack_bf16((j <= i && i < n) ? a[jj] : 0.f, (j + 1 <= i && i < n) ? a[jj + 1] : 0.f);
                 }
-                uint4* dst = reinterpret_cast<uint4*>(f.AQK + ch * BT * BT + (size_t)i * BT + cb);
+                bf16* dst = f.AQK + ch * BT * BT;
 #pragma unroll
-                for (int qq = 0; qq < 4; ++qq) dst[qq] = make_uint4(pw[4 * qq], pw[4 * qq + 1], pw[4 * qq + 2], pw[4 * qq + 3]);
+                for (int qq = 0; qq < 4; ++qq)
+                    *reinterpret_cast<uint4*>(dst + tile_el(BT, i, cb + 8 * qq)) =
+                        make_uint4(pw[4 * qq], pw[4 * qq + 1], pw[4 * qq + 2], pw[4 * qq + 3]);
             }
         }
         __syncthreads();
@@ -322,8 +326,8 @@ __global__ void __launch_bounds__(PT, 2)
             *reinterpret_cast<uint4*>(base + P_BB + tc::sw128_off(BT, lane, 2 * cb)) = make_uint4(b0[0], b0[1], b0[2], b0[3]);
             *reinterpret_cast<uint4*>(base + P_BB + tc::sw128_off(BT, lane + 32, 2 * cb)) = make_uint4(b1[0], b1[1], b1[2], b1[3]);
             if (BWD) {
-                *reinterpret_cast<uint4*>(f.AI + ch * BT * BT + (size_t)lane * BT + cb) = va0;
-                *reinterpret_cast<uint4*>(f.AI + ch * BT * BT + (size_t)(lane + 32) * BT + cb) = va1;
+                *reinterpret_cast<uint4*>(f.AI + ch * BT * BT + tile_el(BT, lane, cb)) = va0;
+                *reinterpret_cast<uint4*>(f.AI + ch * BT * BT + tile_el(BT, lane + 32, cb)) = va1;
             }
         }
         tc::fence_async_smem();
@@ -372,7 +376,7 @@ __global__ void __launch_bounds__(PT, 2)
             __syncthreads();
             for (int idx = tid; idx < BT * 16; idx += PT) {
                 const int i = idx >> 4, cc8 = (idx & 15) * 8;
-                *reinterpret_cast<uint4*>(f.W + ch * BT * D + (size_t)i * D + cc8) = *reinterpret_cast<const uint4*>(sW + i * LW + cc8);
+                *reinterpret_cast<uint4*>(f.W + ch * BT * D + tile_el(BT, i, cc8)) = *reinterpret_cast<const uint4*>(sW + i * LW + cc8);
             }
         }
     }
@@ -384,10 +388,12 @@ __global__ void __launch_bounds__(PT, 2)
 // ======================================================= k_fwd_scan_tc
 constexpr int ST = 256;  // 8 warps: warps w and w+4 share TMEM lane quarter w%4 and split columns
 
-// Shared-memory map (bytes from the 1024-aligned base).
-constexpr int OFF_AS = 0;                    // S^T bf16 [128][128]   32 KB
-constexpr int OFF_AR = OFF_AS + 32768;       // R^T bf16 [128][64]    16 KB
-constexpr int OFF_STAGE = OFF_AR + 16384;    // two stages
+// Shared-memory map (bytes from the 1024-aligned base). The bf16 copies of S^T
+// and R^T are double-buffered so that the output MMAs of chunk c, issued after
+// its state update, may still read them while chunk c+1 runs.
+constexpr int OFF_AS = 0;                    // 2 x S^T bf16 [128][128]   64 KB
+constexpr int OFF_AR = OFF_AS + 65536;       // 2 x R^T bf16 [128][64]    32 KB
+constexpr int OFF_STAGE = OFF_AR + 32768;    // two stages
 constexpr int STG_W = 0;                     // W   [64][128]  16 KB
 constexpr int STG_KG = 16384;                // F   [64][128]  16 KB (read MN-major)
 constexpr int STG_QG = 32768;                // Q_g [64][128]  16 KB
@@ -397,30 +403,40 @@ constexpr int OFF_LAM = OFF_STAGE + 2 * STG_BYTES;   // lambda [128] fp32
 constexpr int OFF_TST = OFF_LAM + 512;                 // per-warp transpose staging, 8 x 1280 B
 constexpr int OFF_BAR = OFF_TST + 8 * 1280;
 constexpr int SCAN_SMEM = OFF_BAR + 64 + 1024;
+static_assert(SCAN_SMEM <= 232448, "scan shared memory above the per-block limit");
 
-using tc::cp_async16;
-using tc::cp_async_commit;
-using tc::cp_async_wait_all;
+// TMEM columns: S^T [0,128), D1 = S^T W^T [128,192), O^T double buffer [192,256) and [256,320)
+constexpr int T_D1 = 128, T_O = 192;
 
-// Copies a row-major bf16 [R][C] global tile into a K-major SW128 smem tile.
-template <int R, int C>
-__device__ __forceinline__ void load_tile(uint32_t sbase, const bf16* src, int tid) {
-    constexpr int CPR = C * 2 / 16;  // 16-byte chunks per row
-    for (int idx = tid; idx < R * CPR; idx += ST) {
-        const int r = idx / CPR, cc = idx % CPR;
-        cp_async16(sbase + tc::sw128_off(R, r, cc * 16), src + (size_t)r * C + cc * 8);
+// Stages the operand tiles of one chunk (stored as tile images) with bulk
+// copies; one thread; completion arrives on `full` as transaction bytes.
+template <int MODE>
+__device__ __forceinline__ void fscan_fill(uint32_t stg, const FwdTC& f, size_t ch, uint64_t* full) {
+    constexpr uint32_t TILE = BT * D * 2, TQ = BT * BT * 2;
+    tc::mbar_arrive_expect_tx(full, (MODE & 1) ? 3 * TILE + TQ : 2 * TILE);
+    tc::bulk_g2s(stg + STG_W, f.W + ch * BT * D, TILE, full);
+    tc::bulk_g2s(stg + STG_KG, f.KG + ch * BT * D, TILE, full);
+    if (MODE & 1) {
+        tc::bulk_g2s(stg + STG_QG, f.QG + ch * BT * D, TILE, full);
+        tc::bulk_g2s(stg + STG_AQ, f.AQK + ch * BT * BT, TQ, full);
     }
 }
 
-template <int MODE>
-__device__ __forceinline__ void fscan_prefetch(uint32_t stg, const FwdTC& f, size_t ch, int tid) {
-    load_tile<BT, D>(stg + STG_W, f.W + ch * BT * D, tid);
-    load_tile<BT, D>(stg + STG_KG, f.KG + ch * BT * D, tid);
-    if (MODE & 1) {
-        load_tile<BT, D>(stg + STG_QG, f.QG + ch * BT * D, tid);
-        load_tile<BT, BT>(stg + STG_AQ, f.AQK + ch * BT * BT, tid);
+// Rows [ib, ib+32) of the output of chunk c from O^T in TMEM (this thread: value column vcol).
+__device__ __forceinline__ void fscan_store_out(uint32_t tl_o, const Table& t, int c, int H, int h, int ib,
+                                                int quad, int lane, bf16* tst, bf16* __restrict__ o) {
+    const int len = t.chunk_len[c], tok0 = t.chunk_tok0[c];
+    float ov[2][16];
+    tc::tmem_ld16(tl_o + ib, ov[0]);
+    tc::tmem_ld16(tl_o + ib + 16, ov[1]);
+    tc::tmem_wait_ld();
+#pragma unroll
+    for (int cq = 0; cq < 32; cq += 16) {
+        const int r0 = ib + cq;
+        if (r0 < len)
+            tc::warp_store_t16(tst, ov[cq / 16], o + ((size_t)(tok0 + r0) * H + h) * D + 32 * quad, (size_t)H * D,
+                               len - r0, lane);
     }
-    cp_async_commit();
 }
 
 template <int MODE>
@@ -430,8 +446,9 @@ __global__ void __launch_bounds__(ST, 1)
     extern __shared__ unsigned char smem_raw[];
     unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                            ~static_cast<uintptr_t>(1023));
-    uint64_t* bar = reinterpret_cast<uint64_t*>(base + OFF_BAR);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 3);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(base + OFF_BAR);   // D1, state update, output
+    uint64_t* full = bar + 3;                                        // operand stages 0, 1
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 5);
     float* sLam = reinterpret_cast<float*>(base + OFF_LAM);
     const uint32_t sb = tc::smem_u32(base);
     const int nseq = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -442,16 +459,15 @@ __global__ void __launch_bounds__(ST, 1)
     const int c0 = t.seq_chunk0[nseq], c1 = t.seq_chunk0[nseq + 1];
 
     if (tid == 0) {
-        tc::mbar_init(&bar[0], 1);
-        tc::mbar_init(&bar[1], 1);
-        tc::mbar_init(&bar[2], 1);
+        for (int i = 0; i < 5; ++i) tc::mbar_init(&bar[i], 1);
         tc::fence_mbar_init();
+        if (c0 < c1) fscan_fill<MODE>(sb + OFF_STAGE, f, (size_t)c0 * H + h, &full[0]);
     }
+    int filled = c0 < c1 ? 1 : 0, waited = 0;   // bulk fills issued / consumed (thread 0)
     if (warp == 0) {
-        tc::tmem_alloc(tslot, 256);
+        tc::tmem_alloc(tslot, 512);
         tc::tmem_relinquish();
     }
-    if (c0 < c1) fscan_prefetch<MODE>(sb + OFF_STAGE, f, (size_t)c0 * H + h, tid);
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
@@ -476,8 +492,8 @@ __global__ void __launch_bounds__(ST, 1)
     for (int c = c0; c < c1 && ok; ++c) {
         const int it = c - c0, stage = it & 1;
         const size_t ch = (size_t)c * H + h;
-        const int len = t.chunk_len[c], tok0 = t.chunk_tok0[c];
         const uint32_t stg = sb + OFF_STAGE + stage * STG_BYTES;
+        const uint32_t aS = sb + OFF_AS + stage * 32768, aR = sb + OFF_AR + stage * 16384;
         // U rows of this thread's value column (consumed after the first MMA)
         float u[32];
         const float* U = f.U + ch * BT * D + (size_t)ib * D + vcol;
@@ -487,109 +503,115 @@ __global__ void __launch_bounds__(ST, 1)
         __syncthreads();
         // 1. S^T -> bf16 operand (and the saved state), then S^T <- S^T diag(lambda);
         //    the four TMEM loads are issued before a single wait
-        float sv[4][16];
+        {
+            float sv[4][16];
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) tc::tmem_ld16(tl + kb + 16 * q4, sv[q4]);
-        tc::tmem_wait_ld();
+            for (int q4 = 0; q4 < 4; ++q4) tc::tmem_ld16(tl + kb + 16 * q4, sv[q4]);
+            tc::tmem_wait_ld();
+            unsigned char* as = base + OFF_AS + stage * 32768;
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-            const int cb = kb + 16 * q4;
-            float (&a)[16] = sv[q4];
-            uint32_t pw[8];
+            for (int q4 = 0; q4 < 4; ++q4) {
+                const int cb = kb + 16 * q4;
+                float (&a)[16] = sv[q4];
+                uint32_t pw[8];
 #pragma unroll
-            for (int jj = 0; jj < 8; ++jj) pw[jj] = tc::pack_bf16(a[2 * jj], a[2 * jj + 1]);
-            *reinterpret_cast<uint4*>(base + OFF_AS + tc::sw128_off(D, vcol, cb * 2)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
-            *reinterpret_cast<uint4*>(base + OFF_AS + tc::sw128_off(D, vcol, cb * 2 + 16)) = make_uint4(pw[4], pw[5], pw[6], pw[7]);
-            if (MODE & 2) tc::warp_store_t16(tst, a, f.HS + ch * D * D + (size_t)cb * D + 32 * quad, D, 16, lane);
+                for (int jj = 0; jj < 8; ++jj) pw[jj] = tc::pack_bf16(a[2 * jj], a[2 * jj + 1]);
+                *reinterpret_cast<uint4*>(as + tc::sw128_off(D, vcol, cb * 2)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+                *reinterpret_cast<uint4*>(as + tc::sw128_off(D, vcol, cb * 2 + 16)) = make_uint4(pw[4], pw[5], pw[6], pw[7]);
+                if (MODE & 2) tc::warp_store_t16(tst, a, f.HS + ch * D * D + (size_t)cb * D + 32 * quad, D, 16, lane);
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) a[jj] *= sLam[cb + jj];
-            tc::tmem_st16(tl + cb, a);
+                for (int jj = 0; jj < 16; ++jj) a[jj] *= sLam[cb + jj];
+                tc::tmem_st16(tl + cb, a);
+            }
         }
         tc::tmem_wait_st();
-        cp_async_wait_all();
         tc::fence_async_smem();
         tc::fence_before_sync();
         __syncthreads();
-        // 2. D1 = S^T W^T ; O^T = S^T Q_g^T
+        // 2. D1 = S^T W^T (the only MMA on the state's critical path before R)
         if (tid == 0) {
             tc::fence_after_sync();
+            if (!tc::mbar_wait(&full[stage], (it >> 1) & 1)) atomicOr(t.err, 2);
+            ++waited;
             const uint32_t id = tc::idesc_bf16(128, 64);
-            const uint32_t aS = sb + OFF_AS;
 #pragma unroll 1
             for (int ks = 0; ks < 8; ++ks)
-                tc::mma_bf16(tb + 128, tc::sdesc_k(aS, D, ks), tc::sdesc_k(stg + STG_W, BT, ks), id, ks > 0);
+                tc::mma_bf16(tb + T_D1, tc::sdesc_k(aS, D, ks), tc::sdesc_k(stg + STG_W, BT, ks), id, ks > 0);
             tc::mma_commit(&bar[0]);
-            if (MODE & 1) {
-#pragma unroll 1
-                for (int ks = 0; ks < 8; ++ks)
-                    tc::mma_bf16(tb + 192, tc::sdesc_k(aS, D, ks), tc::sdesc_k(stg + STG_QG, BT, ks), id, ks > 0);
+        }
+        // while it runs: the output of chunk c-1, then the operands of chunk c+1 (their stage was
+        // last read by the MMAs of chunk c-1, all complete once the output barrier has passed)
+        if (MODE & 1) {
+            if (it > 0) {
+                ok = wait_all(&bar[2], ph2, t.err);
+                ph2 ^= 1;
+                if (!ok) break;
+                tc::fence_after_sync();
+                fscan_store_out(tl + T_O + 64 * ((it - 1) & 1), t, c - 1, H, h, ib, quad, lane, tst, o);
             }
         }
-        // prefetch chunk c+1 into the other stage (its previous MMAs have completed)
-        if (c + 1 < c1) fscan_prefetch<MODE>(sb + OFF_STAGE + (stage ^ 1) * STG_BYTES, f, (size_t)(c + 1) * H + h, tid);
+        if (c + 1 < c1 && tid == 0) {
+            fscan_fill<MODE>(sb + OFF_STAGE + (stage ^ 1) * STG_BYTES, f, (size_t)(c + 1) * H + h, &full[stage ^ 1]);
+            ++filled;
+        }
         ok = wait_all(&bar[0], ph0, t.err);
         ph0 ^= 1;
         if (!ok) break;
         tc::fence_after_sync();
         // 3. R^T = U^T - D1 (bf16 operand; saved for the backward)
-        float rv[2][16];
-        tc::tmem_ld16(tl + 128 + ib, rv[0]);
-        tc::tmem_ld16(tl + 128 + ib + 16, rv[1]);
-        tc::tmem_wait_ld();
+        {
+            float rv[2][16];
+            tc::tmem_ld16(tl + T_D1 + ib, rv[0]);
+            tc::tmem_ld16(tl + T_D1 + ib + 16, rv[1]);
+            tc::tmem_wait_ld();
+            unsigned char* ar = base + OFF_AR + stage * 16384;
 #pragma unroll
-        for (int cq = 0; cq < 32; cq += 16) {
-            float (&a)[16] = rv[cq / 16];
+            for (int cq = 0; cq < 32; cq += 16) {
+                float (&a)[16] = rv[cq / 16];
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) a[jj] = u[cq + jj] - a[jj];
-            uint32_t pw[8];
+                for (int jj = 0; jj < 16; ++jj) a[jj] = u[cq + jj] - a[jj];
+                uint32_t pw[8];
 #pragma unroll
-            for (int jj = 0; jj < 8; ++jj) pw[jj] = tc::pack_bf16(a[2 * jj], a[2 * jj + 1]);
-            *reinterpret_cast<uint4*>(base + OFF_AR + tc::sw128_off(D, vcol, (ib + cq) * 2)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
-            *reinterpret_cast<uint4*>(base + OFF_AR + tc::sw128_off(D, vcol, (ib + cq) * 2 + 16)) = make_uint4(pw[4], pw[5], pw[6], pw[7]);
-            if (MODE & 2) tc::warp_store_t16(tst, a, f.R + ch * BT * D + (size_t)(ib + cq) * D + 32 * quad, D, 16, lane);
+                for (int jj = 0; jj < 8; ++jj) pw[jj] = tc::pack_bf16(a[2 * jj], a[2 * jj + 1]);
+                *reinterpret_cast<uint4*>(ar + tc::sw128_off(D, vcol, (ib + cq) * 2)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+                *reinterpret_cast<uint4*>(ar + tc::sw128_off(D, vcol, (ib + cq) * 2 + 16)) = make_uint4(pw[4], pw[5], pw[6], pw[7]);
+                if (MODE & 2) tc::warp_store_t16(tst, a, f.R + ch * BT * D + (size_t)(ib + cq) * D + 32 * quad, D, 16, lane);
+            }
         }
         tc::fence_async_smem();
         tc::fence_before_sync();
         __syncthreads();
-        // 4. O^T += R^T C_q^T (committed first, so its read-back overlaps the state update);
-        //    S^T += R^T F
+        // 4. S^T += R^T F first (it gates the next chunk), then O^T = S^T Q_g^T + R^T C_q^T into
+        //    this chunk's output buffer, read back during the next chunk
         if (tid == 0) {
             tc::fence_after_sync();
-            const uint32_t aR = sb + OFF_AR;
-            if (MODE & 1) {
-#pragma unroll 1
-                for (int ks = 0; ks < 4; ++ks)
-                    tc::mma_bf16(tb + 192, tc::sdesc_k(aR, D, ks), tc::sdesc_k(stg + STG_AQ, BT, ks), tc::idesc_bf16(128, 64), 1);
-                tc::mma_commit(&bar[2]);
-            }
 #pragma unroll 1
             for (int ks = 0; ks < 4; ++ks)
                 tc::mma_bf16(tb, tc::sdesc_k(aR, D, ks), tc::sdesc_mn(stg + STG_KG, BT * 128, ks), tc::idesc_bf16_bmn(128, 128), 1);
             tc::mma_commit(&bar[1]);
-        }
-        // 5. output rows of this value column
-        if (MODE & 1) {
-            ok = wait_all(&bar[2], ph2, t.err);
-            ph2 ^= 1;
-            if (!ok) break;
-            tc::fence_after_sync();
-            float ov[2][16];
-            tc::tmem_ld16(tl + 192 + ib, ov[0]);
-            tc::tmem_ld16(tl + 192 + ib + 16, ov[1]);
-            tc::tmem_wait_ld();
-#pragma unroll
-            for (int cq = 0; cq < 32; cq += 16) {
-                const int r0 = ib + cq;
-                if (r0 < len)
-                    tc::warp_store_t16(tst, ov[cq / 16], o + ((size_t)(tok0 + r0) * H + h) * D + 32 * quad,
-                                       (size_t)H * D, len - r0, lane);
+            if (MODE & 1) {
+                const uint32_t tO = tb + T_O + 64 * stage, id = tc::idesc_bf16(128, 64);
+#pragma unroll 1
+                for (int ks = 0; ks < 8; ++ks)
+                    tc::mma_bf16(tO, tc::sdesc_k(aS, D, ks), tc::sdesc_k(stg + STG_QG, BT, ks), id, ks > 0);
+#pragma unroll 1
+                for (int ks = 0; ks < 4; ++ks)
+                    tc::mma_bf16(tO, tc::sdesc_k(aR, D, ks), tc::sdesc_k(stg + STG_AQ, BT, ks), id, 1);
+                tc::mma_commit(&bar[2]);
             }
-            tc::fence_before_sync();
         }
         ok = wait_all(&bar[1], ph1, t.err);
         ph1 ^= 1;
         if (!ok) break;
         tc::fence_after_sync();
+    }
+    // output of the last chunk
+    if ((MODE & 1) && ok && c1 > c0) {
+        ok = wait_all(&bar[2], ph2, t.err);
+        if (ok) {
+            tc::fence_after_sync();
+            fscan_store_out(tl + T_O + 64 * ((c1 - 1 - c0) & 1), t, c1 - 1, H, h, ib, quad, lane, tst, o);
+        }
     }
     if (ok && ht) {
         tc::fence_after_sync();
@@ -602,10 +624,12 @@ __global__ void __launch_bounds__(ST, 1)
             for (int jj = 0; jj < 16; ++jj) ht[st_off + (size_t)(cb + jj) * D + vcol] = a[jj];
         }
     }
-    cp_async_wait_all();
+    // after an early exit, let a bulk fill still in flight land before the CTA leaves
+    if (tid == 0)
+        for (; waited < filled; ++waited) tc::mbar_wait(&full[waited & 1], (waited >> 1) & 1);
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 0) tc::tmem_dealloc(tb, 256);
+    if (warp == 0) tc::tmem_dealloc(tb, 512);
 }
 
 

@@ -114,6 +114,16 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                  : "memory");
 }
 
+// Bulk copy (TMA, no tensor map) of `bytes` contiguous bytes global -> shared;
+// completion is signalled as transaction bytes on `bar`. Both addresses
+// 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // ------------------------------------------------------------------- fences
 // Generic-proxy shared-memory writes -> visible to the async proxy (MMA, TMA).
 __device__ __forceinline__ void fence_async_smem() {
@@ -231,7 +241,6 @@ __device__ __forceinline__ void warp_store_t16(__nv_bfloat16* stg, const float (
     __syncwarp();
 }
 
-// bf16 pair packing
 // Approximate reciprocal (the PTX rcp.approx instruction, about 1 ulp); for
 // operands that are rounded to bf16 afterwards.
 __device__ __forceinline__ float rcp_approx(float x) {
@@ -240,6 +249,7 @@ __device__ __forceinline__ float rcp_approx(float x) {
     return y;
 }
 
+// bf16 pair packing
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 t = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&t);
