@@ -386,7 +386,13 @@ __global__ void __launch_bounds__(PT, 2)
 }
 
 // ======================================================= k_fwd_scan_tc
-constexpr int ST = 256;  // 8 warps: warps w and w+4 share TMEM lane quarter w%4 and split columns
+constexpr int ST = 256;            // compute warps: warps w and w+4 share TMEM lane quarter w%4
+constexpr int ST_ALL = ST + 32;    // + one warp that issues the MMAs and the bulk fills
+// Named barriers; compute warps and the issuer meet on each (also keeping them
+// in lockstep if an MMA wait ever times out).
+constexpr int NB_AS = 1;           // S^T staged for D1
+constexpr int NB_AR = 2;           // R^T staged for the state update and the output
+constexpr int NB_C = 3;            //                compute warps only
 
 // Shared-memory map (bytes from the 1024-aligned base). The bf16 copies of S^T
 // and R^T are double-buffered so that the output MMAs of chunk c, issued after
@@ -439,40 +445,22 @@ __device__ __forceinline__ void fscan_store_out(uint32_t tl_o, const Table& t, i
     }
 }
 
+// Compute warps: every per-element pass over S^T, D1, R^T and O^T. The work
+// that gates the next MMA (the bf16 copies of S^T and R^T) comes first and is
+// handed over on a named barrier; the rest (lambda scaling of S^T, saved
+// states, the previous chunk's output) overlaps the MMA that follows.
 template <int MODE>
-__global__ void __launch_bounds__(ST, 1)
-    k_fwd_scan_tc(Shape s, const float* __restrict__ h0, Table t, FwdTC f, bf16* __restrict__ o,
-                  float* __restrict__ ht) {
-    extern __shared__ unsigned char smem_raw[];
-    unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                           ~static_cast<uintptr_t>(1023));
-    uint64_t* bar = reinterpret_cast<uint64_t*>(base + OFF_BAR);   // D1, state update, output
-    uint64_t* full = bar + 3;                                        // operand stages 0, 1
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 5);
-    float* sLam = reinterpret_cast<float*>(base + OFF_LAM);
-    const uint32_t sb = tc::smem_u32(base);
-    const int nseq = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+__device__ __forceinline__ void fscan_compute(const Shape& s, const float* __restrict__ h0, const Table& t,
+                                              const FwdTC& f, bf16* __restrict__ o, float* __restrict__ ht,
+                                              unsigned char* base, uint64_t* bar, uint32_t tb, int nseq, int h,
+                                              int c0, int c1) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = warp & 3, half = warp >> 2;
+    float* sLam = reinterpret_cast<float*>(base + OFF_LAM);
     bf16* tst = reinterpret_cast<bf16*>(base + OFF_TST + warp * 1280);
     const int H = s.H;
     const int vcol = 32 * quad + lane;  // TMEM lane and value column of this thread
-    const int c0 = t.seq_chunk0[nseq], c1 = t.seq_chunk0[nseq + 1];
-
-    if (tid == 0) {
-        for (int i = 0; i < 5; ++i) tc::mbar_init(&bar[i], 1);
-        tc::fence_mbar_init();
-        if (c0 < c1) fscan_fill<MODE>(sb + OFF_STAGE, f, (size_t)c0 * H + h, &full[0]);
-    }
-    int filled = c0 < c1 ? 1 : 0, waited = 0;   // bulk fills issued / consumed (thread 0)
-    if (warp == 0) {
-        tc::tmem_alloc(tslot, 512);
-        tc::tmem_relinquish();
-    }
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-    const uint32_t tb = *tslot;
-    const uint32_t tl = tc::taddr(tb, 32 * quad, 0);  // this warp's lane quarter
+    const uint32_t tl = tc::taddr(tb, 32 * quad, 0);
     const size_t st_off = ((size_t)nseq * H + h) * D * D;
     const int kb = 64 * half;   // this thread's half of the key columns of S^T
     const int ib = 32 * half;   // this thread's half of the chunk rows
@@ -487,49 +475,117 @@ __global__ void __launch_bounds__(ST, 1)
     }
     tc::tmem_wait_st();
 
-    uint32_t ph0 = 0, ph1 = 0, ph2 = 0;
     bool ok = true;
-    for (int c = c0; c < c1 && ok; ++c) {
+    auto wait_one = [&](uint64_t* b, uint32_t parity) {
+        if (ok && !tc::mbar_wait(b, parity)) {
+            ok = false;
+            atomicOr(t.err, 2);
+        }
+        tc::fence_after_sync();
+    };
+    for (int c = c0; c < c1; ++c) {
         const int it = c - c0, stage = it & 1;
         const size_t ch = (size_t)c * H + h;
-        const uint32_t stg = sb + OFF_STAGE + stage * STG_BYTES;
-        const uint32_t aS = sb + OFF_AS + stage * 32768, aR = sb + OFF_AR + stage * 16384;
-        // U rows of this thread's value column (consumed after the first MMA)
+        unsigned char* as = base + OFF_AS + stage * 32768;
+        unsigned char* ar = base + OFF_AR + stage * 16384;
+        // U rows of this thread's value column (consumed in the R pass)
         float u[32];
         const float* U = f.U + ch * BT * D + (size_t)ib * D + vcol;
 #pragma unroll
         for (int i = 0; i < 32; ++i) u[i] = U[(size_t)i * D];
         if (tid < D) sLam[tid] = exp2f(f.GL[ch * D + tid]);
-        __syncthreads();
-        // 1. S^T -> bf16 operand (and the saved state), then S^T <- S^T diag(lambda);
-        //    the four TMEM loads are issued before a single wait
-        {
-            float sv[4][16];
+        if (it > 0) wait_one(&bar[1], (it - 1) & 1);   // the state update of chunk c-1
+        tc::named_sync(NB_C, ST);
+        // 1. S^T -> bf16 operand of D1 = S^T W^T, handed to the issuer
+        float sv[4][16];
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) tc::tmem_ld16(tl + kb + 16 * q4, sv[q4]);
-            tc::tmem_wait_ld();
-            unsigned char* as = base + OFF_AS + stage * 32768;
+        for (int q4 = 0; q4 < 4; ++q4) tc::tmem_ld16(tl + kb + 16 * q4, sv[q4]);
+        tc::tmem_wait_ld();
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                const int cb = kb + 16 * q4;
-                float (&a)[16] = sv[q4];
-                uint32_t pw[8];
+        for (int q4 = 0; q4 < 4; ++q4) {
+            const int cb = kb + 16 * q4;
+            uint32_t pw[8];
 #pragma unroll
-                for (int jj = 0; jj < 8; ++jj) pw[jj] = tc::pack_bf16(a[2 * jj], a[2 * jj + 1]);
-                *reinterpret_cast<uint4*>(as + tc::sw128_off(D, vcol, cb * 2)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
-                *reinterpret_cast<uint4*>(as + tc::sw128_off(D, vcol, cb * 2 + 16)) = make_uint4(pw[4], pw[5], pw[6], pw[7]);
-                if (MODE & 2) tc::warp_store_t16(tst, a, f.HS + ch * D * D + (size_t)cb * D + 32 * quad, D, 16, lane);
-#pragma unroll
-                for (int jj = 0; jj < 16; ++jj) a[jj] *= sLam[cb + jj];
-                tc::tmem_st16(tl + cb, a);
-            }
+            for (int jj = 0; jj < 8; ++jj) pw[jj] = tc::pack_bf16(sv[q4][2 * jj], sv[q4][2 * jj + 1]);
+            *reinterpret_cast<uint4*>(as + tc::sw128_off(D, vcol, cb * 2)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+            *reinterpret_cast<uint4*>(as + tc::sw128_off(D, vcol, cb * 2 + 16)) = make_uint4(pw[4], pw[5], pw[6], pw[7]);
         }
-        tc::tmem_wait_st();
         tc::fence_async_smem();
         tc::fence_before_sync();
-        __syncthreads();
-        // 2. D1 = S^T W^T (the only MMA on the state's critical path before R)
-        if (tid == 0) {
+        tc::named_sync(NB_AS, ST_ALL);
+        // 2. while D1 runs: the saved state, S^T <- S^T diag(lambda), the output of chunk c-1
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+            const int cb = kb + 16 * q4;
+            if (MODE & 2) tc::warp_store_t16(tst, sv[q4], f.HS + ch * D * D + (size_t)cb * D + 32 * quad, D, 16, lane);
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) sv[q4][jj] *= sLam[cb + jj];
+            tc::tmem_st16(tl + cb, sv[q4]);
+        }
+        tc::tmem_wait_st();
+        if ((MODE & 1) && it > 0) {
+            wait_one(&bar[2], (it - 1) & 1);
+            fscan_store_out(tl + T_O + 64 * ((it - 1) & 1), t, c - 1, H, h, ib, quad, lane, tst, o);
+        }
+        // 3. R^T = U^T - D1 -> bf16 operand of the state update and the output, handed over
+        wait_one(&bar[0], it & 1);
+        float rv[2][16];
+        tc::tmem_ld16(tl + T_D1 + ib, rv[0]);
+        tc::tmem_ld16(tl + T_D1 + ib + 16, rv[1]);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int cq = 0; cq < 32; cq += 16) {
+            float (&a)[16] = rv[cq / 16];
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) a[jj] = u[cq + jj] - a[jj];
+            uint32_t pw[8];
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) pw[jj] = tc::pack_bf16(a[2 * jj], a[2 * jj + 1]);
+            *reinterpret_cast<uint4*>(ar + tc::sw128_off(D, vcol, (ib + cq) * 2)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+            *reinterpret_cast<uint4*>(ar + tc::sw128_off(D, vcol, (ib + cq) * 2 + 16)) = make_uint4(pw[4], pw[5], pw[6], pw[7]);
+        }
+        tc::fence_async_smem();
+        tc::fence_before_sync();
+        tc::named_sync(NB_AR, ST_ALL);
+        if (MODE & 2) {
+#pragma unroll
+            for (int cq = 0; cq < 32; cq += 16)
+                tc::warp_store_t16(tst, rv[cq / 16], f.R + ch * BT * D + (size_t)(ib + cq) * D + 32 * quad, D, 16, lane);
+        }
+    }
+    if (c1 > c0) {
+        const int last = c1 - 1 - c0;
+        wait_one(&bar[1], last & 1);
+        if (MODE & 1) {
+            wait_one(&bar[2], last & 1);
+            fscan_store_out(tl + T_O + 64 * (last & 1), t, c1 - 1, H, h, ib, quad, lane, tst, o);
+        }
+    }
+    if (ok && ht) {
+#pragma unroll 1
+        for (int cb = kb; cb < kb + 64; cb += 16) {
+            float a[16];
+            tc::tmem_ld16(tl + cb, a);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) ht[st_off + (size_t)(cb + jj) * D + vcol] = a[jj];
+        }
+    }
+}
+
+// Issuer warp: bulk fills of the operand stages and every MMA (lane 0).
+template <int MODE>
+__device__ __forceinline__ void fscan_issue(const Shape& s, const Table& t, const FwdTC& f, uint32_t sb,
+                                            uint64_t* bar, uint64_t* full, uint32_t tb, int h, int c0, int c1,
+                                            int& filled, int& waited) {
+    const int lane = threadIdx.x & 31;
+    const int H = s.H;
+    for (int c = c0; c < c1; ++c) {
+        const int it = c - c0, stage = it & 1;
+        const uint32_t stg = sb + OFF_STAGE + stage * STG_BYTES;
+        const uint32_t aS = sb + OFF_AS + stage * 32768, aR = sb + OFF_AR + stage * 16384;
+        tc::named_sync(NB_AS, ST_ALL);
+        if (lane == 0) {
             tc::fence_after_sync();
             if (!tc::mbar_wait(&full[stage], (it >> 1) & 1)) atomicOr(t.err, 2);
             ++waited;
@@ -538,56 +594,24 @@ __global__ void __launch_bounds__(ST, 1)
             for (int ks = 0; ks < 8; ++ks)
                 tc::mma_bf16(tb + T_D1, tc::sdesc_k(aS, D, ks), tc::sdesc_k(stg + STG_W, BT, ks), id, ks > 0);
             tc::mma_commit(&bar[0]);
-        }
-        // while it runs: the output of chunk c-1, then the operands of chunk c+1 (their stage was
-        // last read by the MMAs of chunk c-1, all complete once the output barrier has passed)
-        if (MODE & 1) {
-            if (it > 0) {
-                ok = wait_all(&bar[2], ph2, t.err);
-                ph2 ^= 1;
-                if (!ok) break;
-                tc::fence_after_sync();
-                fscan_store_out(tl + T_O + 64 * ((it - 1) & 1), t, c - 1, H, h, ib, quad, lane, tst, o);
+            if (c + 1 < c1) {
+                // the other stage is free once every MMA of chunk c-1 has completed (a commit
+                // covers all earlier MMAs of this thread)
+                if (it > 0 && !tc::mbar_wait(&bar[(MODE & 1) ? 2 : 1], (it - 1) & 1)) atomicOr(t.err, 2);
+                fscan_fill<MODE>(sb + OFF_STAGE + (stage ^ 1) * STG_BYTES, f, (size_t)(c + 1) * H + h,
+                                 &full[stage ^ 1]);
+                ++filled;
             }
         }
-        if (c + 1 < c1 && tid == 0) {
-            fscan_fill<MODE>(sb + OFF_STAGE + (stage ^ 1) * STG_BYTES, f, (size_t)(c + 1) * H + h, &full[stage ^ 1]);
-            ++filled;
-        }
-        ok = wait_all(&bar[0], ph0, t.err);
-        ph0 ^= 1;
-        if (!ok) break;
-        tc::fence_after_sync();
-        // 3. R^T = U^T - D1 (bf16 operand; saved for the backward)
-        {
-            float rv[2][16];
-            tc::tmem_ld16(tl + T_D1 + ib, rv[0]);
-            tc::tmem_ld16(tl + T_D1 + ib + 16, rv[1]);
-            tc::tmem_wait_ld();
-            unsigned char* ar = base + OFF_AR + stage * 16384;
-#pragma unroll
-            for (int cq = 0; cq < 32; cq += 16) {
-                float (&a)[16] = rv[cq / 16];
-#pragma unroll
-                for (int jj = 0; jj < 16; ++jj) a[jj] = u[cq + jj] - a[jj];
-                uint32_t pw[8];
-#pragma unroll
-                for (int jj = 0; jj < 8; ++jj) pw[jj] = tc::pack_bf16(a[2 * jj], a[2 * jj + 1]);
-                *reinterpret_cast<uint4*>(ar + tc::sw128_off(D, vcol, (ib + cq) * 2)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
-                *reinterpret_cast<uint4*>(ar + tc::sw128_off(D, vcol, (ib + cq) * 2 + 16)) = make_uint4(pw[4], pw[5], pw[6], pw[7]);
-                if (MODE & 2) tc::warp_store_t16(tst, a, f.R + ch * BT * D + (size_t)(ib + cq) * D + 32 * quad, D, 16, lane);
-            }
-        }
-        tc::fence_async_smem();
-        tc::fence_before_sync();
-        __syncthreads();
-        // 4. S^T += R^T F first (it gates the next chunk), then O^T = S^T Q_g^T + R^T C_q^T into
-        //    this chunk's output buffer, read back during the next chunk
-        if (tid == 0) {
+        __syncwarp();
+        tc::named_sync(NB_AR, ST_ALL);
+        if (lane == 0) {
             tc::fence_after_sync();
+            // S^T += R^T F first (it gates the next chunk), then O^T = S^T Q_g^T + R^T C_q^T
 #pragma unroll 1
             for (int ks = 0; ks < 4; ++ks)
-                tc::mma_bf16(tb, tc::sdesc_k(aR, D, ks), tc::sdesc_mn(stg + STG_KG, BT * 128, ks), tc::idesc_bf16_bmn(128, 128), 1);
+                tc::mma_bf16(tb, tc::sdesc_k(aR, D, ks), tc::sdesc_mn(stg + STG_KG, BT * 128, ks),
+                             tc::idesc_bf16_bmn(128, 128), 1);
             tc::mma_commit(&bar[1]);
             if (MODE & 1) {
                 const uint32_t tO = tb + T_O + 64 * stage, id = tc::idesc_bf16(128, 64);
@@ -600,38 +624,53 @@ __global__ void __launch_bounds__(ST, 1)
                 tc::mma_commit(&bar[2]);
             }
         }
-        ok = wait_all(&bar[1], ph1, t.err);
-        ph1 ^= 1;
-        if (!ok) break;
-        tc::fence_after_sync();
+        __syncwarp();
     }
-    // output of the last chunk
-    if ((MODE & 1) && ok && c1 > c0) {
-        ok = wait_all(&bar[2], ph2, t.err);
-        if (ok) {
-            tc::fence_after_sync();
-            fscan_store_out(tl + T_O + 64 * ((c1 - 1 - c0) & 1), t, c1 - 1, H, h, ib, quad, lane, tst, o);
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(ST_ALL, 1)
+    k_fwd_scan_tc(Shape s, const float* __restrict__ h0, Table t, FwdTC f, bf16* __restrict__ o,
+                  float* __restrict__ ht) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                           ~static_cast<uintptr_t>(1023));
+    uint64_t* bar = reinterpret_cast<uint64_t*>(base + OFF_BAR);   // D1, state update, output
+    uint64_t* full = bar + 3;                                        // operand stages 0, 1
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 5);
+    const uint32_t sb = tc::smem_u32(base);
+    const int nseq = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5;
+    const int c0 = t.seq_chunk0[nseq], c1 = t.seq_chunk0[nseq + 1];
+    const bool issuer = warp == ST / 32;
+    int filled = 0, waited = 0;   // bulk fills issued / consumed (issuer lane 0)
+
+    if (issuer && (tid & 31) == 0) {
+        for (int i = 0; i < 5; ++i) tc::mbar_init(&bar[i], 1);
+        tc::fence_mbar_init();
+        if (c0 < c1) {
+            fscan_fill<MODE>(sb + OFF_STAGE, f, (size_t)c0 * s.H + h, &full[0]);
+            filled = 1;
         }
     }
-    if (ok && ht) {
-        tc::fence_after_sync();
-#pragma unroll 1
-        for (int cb = kb; cb < kb + 64; cb += 16) {
-            float a[16];
-            tc::tmem_ld16(tl + cb, a);
-            tc::tmem_wait_ld();
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj) ht[st_off + (size_t)(cb + jj) * D + vcol] = a[jj];
-        }
+    if (warp == 0) {
+        tc::tmem_alloc(tslot, 512);
+        tc::tmem_relinquish();
     }
-    // after an early exit, let a bulk fill still in flight land before the CTA leaves
-    if (tid == 0)
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tb = *tslot;
+    if (issuer)
+        fscan_issue<MODE>(s, t, f, sb, bar, full, tb, h, c0, c1, filled, waited);
+    else
+        fscan_compute<MODE>(s, h0, t, f, o, ht, base, bar, tb, nseq, h, c0, c1);
+    // a bulk fill still in flight (only after a timeout) lands before the CTA leaves
+    if (issuer && (tid & 31) == 0)
         for (; waited < filled; ++waited) tc::mbar_wait(&full[waited & 1], (waited >> 1) & 1);
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tb, 512);
 }
-
 
 template <int GATE, bool BWD>
 cudaError_t run_prep(const Shape& s, const void* q, const void* k, const void* v, const void* beta,
@@ -649,7 +688,7 @@ cudaError_t run_scan(const Shape& s, const float* h0, Table t, FwdTC f, void* o,
     cudaError_t e = set_smem_once<k_fwd_scan_tc<MODE>>(SCAN_SMEM);
     if (e != cudaSuccess) return e;
     dim3 grid(s.N, s.H);
-    k_fwd_scan_tc<MODE><<<grid, ST, SCAN_SMEM, st>>>(s, h0, t, f, (bf16*)o, ht);
+    k_fwd_scan_tc<MODE><<<grid, ST_ALL, SCAN_SMEM, st>>>(s, h0, t, f, (bf16*)o, ht);
     return cudaGetLastError();
 }
 

@@ -124,6 +124,12 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
         : "memory");
 }
 
+// Named CTA barrier (id 1..15; 0 is __syncthreads): waits for `count` threads
+// (a multiple of 32).
+__device__ __forceinline__ void named_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // ------------------------------------------------------------------- fences
 // Generic-proxy shared-memory writes -> visible to the async proxy (MMA, TMA).
 __device__ __forceinline__ void fence_async_smem() {
