@@ -394,12 +394,8 @@ constexpr int NB_AS = 1;           // S^T staged for D1
 constexpr int NB_AR = 2;           // R^T staged for the state update and the output
 constexpr int NB_C = 3;            //                compute warps only
 
-// Shared-memory map (bytes from the 1024-aligned base). The bf16 copies of S^T
-// and R^T are double-buffered so that the output MMAs of chunk c, issued after
-// its state update, may still read them while chunk c+1 runs.
-constexpr int OFF_AS = 0;                    // 2 x S^T bf16 [128][128]   64 KB
-constexpr int OFF_AR = OFF_AS + 65536;       // 2 x R^T bf16 [128][64]    32 KB
-constexpr int OFF_STAGE = OFF_AR + 32768;    // two stages
+// Shared-memory map (bytes from the 1024-aligned base): the B operands only.
+constexpr int OFF_STAGE = 0;                 // two stages
 constexpr int STG_W = 0;                     // W   [64][128]  16 KB
 constexpr int STG_KG = 16384;                // F   [64][128]  16 KB (read MN-major)
 constexpr int STG_QG = 32768;                // Q_g [64][128]  16 KB
@@ -411,8 +407,12 @@ constexpr int OFF_BAR = OFF_TST + 8 * 1280;
 constexpr int SCAN_SMEM = OFF_BAR + 64 + 1024;
 static_assert(SCAN_SMEM <= 232448, "scan shared memory above the per-block limit");
 
-// TMEM columns: S^T [0,128), D1 = S^T W^T [128,192), O^T double buffer [192,256) and [256,320)
-constexpr int T_D1 = 128, T_O = 192;
+// TMEM columns: S^T fp32 [0,128), D1 = S^T W^T [128,192), O^T double buffer [192,320);
+// the bf16 A operands S^T (64 columns) and R^T (32 columns), double-buffered so
+// that the output MMAs of chunk c, issued after its state update, may still
+// read them while chunk c+1 runs: [320,448) and [448,512). The MMAs then read
+// only their B operands from shared memory.
+constexpr int T_D1 = 128, T_O = 192, T_AS = 320, T_AR = 448;
 
 // Stages the operand tiles of one chunk (stored as tile images) with bulk
 // copies; one thread; completion arrives on `full` as transaction bytes.
@@ -428,10 +428,10 @@ __device__ __forceinline__ void fscan_fill(uint32_t stg, const FwdTC& f, size_t 
     }
 }
 
-// Rows [ib, ib+32) of the output of chunk c from O^T in TMEM (this thread: value column vcol).
-__device__ __forceinline__ void fscan_store_out(uint32_t tl_o, const Table& t, int c, int H, int h, int ib,
+// Rows [ib, ib+32) of the output of a chunk (len tokens from tok0) from O^T in
+// TMEM (this thread: value column vcol).
+__device__ __forceinline__ void fscan_store_out(uint32_t tl_o, int len, int tok0, int H, int h, int ib,
                                                 int quad, int lane, bf16* tst, bf16* __restrict__ o) {
-    const int len = t.chunk_len[c], tok0 = t.chunk_tok0[c];
     float ov[2][16];
     tc::tmem_ld16(tl_o + ib, ov[0]);
     tc::tmem_ld16(tl_o + ib + 16, ov[1]);
@@ -443,6 +443,15 @@ __device__ __forceinline__ void fscan_store_out(uint32_t tl_o, const Table& t, i
             tc::warp_store_t16(tst, ov[cq / 16], o + ((size_t)(tok0 + r0) * H + h) * D + 32 * quad, (size_t)H * D,
                                len - r0, lane);
     }
+}
+
+// Small per-chunk inputs of a compute thread, loaded a chunk ahead: G at the
+// chunk end (threads < D) and the chunk's extent.
+__device__ __forceinline__ void fscan_load_next(const FwdTC& f, const Table& t, int c, int H, int h, int tid,
+                                                float& gln, int& len, int& tok0) {
+    if (tid < D) gln = __ldg(f.GL + ((size_t)c * H + h) * D + tid);
+    len = __ldg(t.chunk_len + c);
+    tok0 = __ldg(t.chunk_tok0 + c);
 }
 
 // Compute warps: every per-element pass over S^T, D1, R^T and O^T. The work
@@ -483,34 +492,38 @@ __device__ __forceinline__ void fscan_compute(const Shape& s, const float* __res
         }
         tc::fence_after_sync();
     };
+    float gln = 0.f;
+    int lenn = 0, tok0n = 0, lenp = 0, tok0p = 0;
+    if (c0 < c1) fscan_load_next(f, t, c0, H, h, tid, gln, lenn, tok0n);
     for (int c = c0; c < c1; ++c) {
         const int it = c - c0, stage = it & 1;
         const size_t ch = (size_t)c * H + h;
-        unsigned char* as = base + OFF_AS + stage * 32768;
-        unsigned char* ar = base + OFF_AR + stage * 16384;
         // U rows of this thread's value column (consumed in the R pass)
         float u[32];
         const float* U = f.U + ch * BT * D + (size_t)ib * D + vcol;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) u[i] = U[(size_t)i * D];
-        if (tid < D) sLam[tid] = exp2f(f.GL[ch * D + tid]);
+        for (int i = 0; i < 32; ++i) u[i] = __ldg(U + (size_t)i * D);
+        const int len = lenn, tok0 = tok0n;
+        if (tid < D) sLam[tid] = exp2f(gln);
+        if (c + 1 < c1) fscan_load_next(f, t, c + 1, H, h, tid, gln, lenn, tok0n);
         if (it > 0) wait_one(&bar[1], (it - 1) & 1);   // the state update of chunk c-1
         tc::named_sync(NB_C, ST);
-        // 1. S^T -> bf16 operand of D1 = S^T W^T, handed to the issuer
+        // 1. S^T -> bf16 A operand of D1 = S^T W^T (TMEM), handed to the issuer
         float sv[4][16];
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) tc::tmem_ld16(tl + kb + 16 * q4, sv[q4]);
         tc::tmem_wait_ld();
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-            const int cb = kb + 16 * q4;
-            uint32_t pw[8];
+        for (int hq = 0; hq < 2; ++hq) {
+            uint32_t pw[16];
 #pragma unroll
-            for (int jj = 0; jj < 8; ++jj) pw[jj] = tc::pack_bf16(sv[q4][2 * jj], sv[q4][2 * jj + 1]);
-            *reinterpret_cast<uint4*>(as + tc::sw128_off(D, vcol, cb * 2)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
-            *reinterpret_cast<uint4*>(as + tc::sw128_off(D, vcol, cb * 2 + 16)) = make_uint4(pw[4], pw[5], pw[6], pw[7]);
+            for (int jj = 0; jj < 8; ++jj) {
+                pw[jj] = tc::pack_bf16(sv[2 * hq][2 * jj], sv[2 * hq][2 * jj + 1]);
+                pw[8 + jj] = tc::pack_bf16(sv[2 * hq + 1][2 * jj], sv[2 * hq + 1][2 * jj + 1]);
+            }
+            tc::tmem_st16u(tl + T_AS + 64 * stage + kb / 2 + 16 * hq, pw);
         }
-        tc::fence_async_smem();
+        tc::tmem_wait_st();
         tc::fence_before_sync();
         tc::named_sync(NB_AS, ST_ALL);
         // 2. while D1 runs: the saved state, S^T <- S^T diag(lambda), the output of chunk c-1
@@ -525,26 +538,28 @@ __device__ __forceinline__ void fscan_compute(const Shape& s, const float* __res
         tc::tmem_wait_st();
         if ((MODE & 1) && it > 0) {
             wait_one(&bar[2], (it - 1) & 1);
-            fscan_store_out(tl + T_O + 64 * ((it - 1) & 1), t, c - 1, H, h, ib, quad, lane, tst, o);
+            fscan_store_out(tl + T_O + 64 * ((it - 1) & 1), lenp, tok0p, H, h, ib, quad, lane, tst, o);
         }
-        // 3. R^T = U^T - D1 -> bf16 operand of the state update and the output, handed over
+        lenp = len;
+        tok0p = tok0;
+        // 3. R^T = U^T - D1 -> bf16 A operand (TMEM) of the state update and the output
         wait_one(&bar[0], it & 1);
         float rv[2][16];
         tc::tmem_ld16(tl + T_D1 + ib, rv[0]);
         tc::tmem_ld16(tl + T_D1 + ib + 16, rv[1]);
         tc::tmem_wait_ld();
+        {
+            uint32_t pw[16];
 #pragma unroll
-        for (int cq = 0; cq < 32; cq += 16) {
-            float (&a)[16] = rv[cq / 16];
+            for (int cq = 0; cq < 2; ++cq) {
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) a[jj] = u[cq + jj] - a[jj];
-            uint32_t pw[8];
+                for (int jj = 0; jj < 16; ++jj) rv[cq][jj] = u[16 * cq + jj] - rv[cq][jj];
 #pragma unroll
-            for (int jj = 0; jj < 8; ++jj) pw[jj] = tc::pack_bf16(a[2 * jj], a[2 * jj + 1]);
-            *reinterpret_cast<uint4*>(ar + tc::sw128_off(D, vcol, (ib + cq) * 2)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
-            *reinterpret_cast<uint4*>(ar + tc::sw128_off(D, vcol, (ib + cq) * 2 + 16)) = make_uint4(pw[4], pw[5], pw[6], pw[7]);
+                for (int jj = 0; jj < 8; ++jj) pw[8 * cq + jj] = tc::pack_bf16(rv[cq][2 * jj], rv[cq][2 * jj + 1]);
+            }
+            tc::tmem_st16u(tl + T_AR + 32 * stage + ib / 2, pw);
         }
-        tc::fence_async_smem();
+        tc::tmem_wait_st();
         tc::fence_before_sync();
         tc::named_sync(NB_AR, ST_ALL);
         if (MODE & 2) {
@@ -558,7 +573,7 @@ __device__ __forceinline__ void fscan_compute(const Shape& s, const float* __res
         wait_one(&bar[1], last & 1);
         if (MODE & 1) {
             wait_one(&bar[2], last & 1);
-            fscan_store_out(tl + T_O + 64 * (last & 1), t, c1 - 1, H, h, ib, quad, lane, tst, o);
+            fscan_store_out(tl + T_O + 64 * (last & 1), lenp, tok0p, H, h, ib, quad, lane, tst, o);
         }
     }
     if (ok && ht) {
@@ -573,30 +588,34 @@ __device__ __forceinline__ void fscan_compute(const Shape& s, const float* __res
     }
 }
 
-// Issuer warp: bulk fills of the operand stages and every MMA (lane 0).
+// Issuer warp: bulk fills of the operand stages (lane 0) and every MMA (the
+// whole warp with warp-uniform descriptors, one elected lane issuing).
 template <int MODE>
 __device__ __forceinline__ void fscan_issue(const Shape& s, const Table& t, const FwdTC& f, uint32_t sb,
                                             uint64_t* bar, uint64_t* full, uint32_t tb, int h, int c0, int c1,
                                             int& filled, int& waited) {
     const int lane = threadIdx.x & 31;
     const int H = s.H;
+    const uint32_t i64 = tc::idesc_bf16(128, 64), i128m = tc::idesc_bf16_bmn(128, 128);
     for (int c = c0; c < c1; ++c) {
         const int it = c - c0, stage = it & 1;
         const uint32_t stg = sb + OFF_STAGE + stage * STG_BYTES;
-        const uint32_t aS = sb + OFF_AS + stage * 32768, aR = sb + OFF_AR + stage * 16384;
+        const uint32_t aS = tb + T_AS + 64 * stage, aR = tb + T_AR + 32 * stage;   // A operands in TMEM
         tc::named_sync(NB_AS, ST_ALL);
-        if (lane == 0) {
-            tc::fence_after_sync();
-            if (!tc::mbar_wait(&full[stage], (it >> 1) & 1)) atomicOr(t.err, 2);
-            ++waited;
-            const uint32_t id = tc::idesc_bf16(128, 64);
-#pragma unroll 1
+        tc::fence_after_sync();
+        if (!tc::mbar_wait(&full[stage], (it >> 1) & 1) && lane == 0) atomicOr(t.err, 2);
+        {
+            const uint64_t dW = tc::sdesc(stg + STG_W);
+#pragma unroll
             for (int ks = 0; ks < 8; ++ks)
-                tc::mma_bf16(tb + T_D1, tc::sdesc_k(aS, D, ks), tc::sdesc_k(stg + STG_W, BT, ks), id, ks > 0);
-            tc::mma_commit(&bar[0]);
+                tc::mma_bf16_ts_w(tb + T_D1, aS + 8 * ks, tc::kstep_k(dW, BT, ks), i64, ks > 0);
+            tc::mma_commit_w(&bar[0]);
+        }
+        if (lane == 0) {
+            ++waited;
             if (c + 1 < c1) {
                 // the other stage is free once every MMA of chunk c-1 has completed (a commit
-                // covers all earlier MMAs of this thread)
+                // covers all earlier MMAs of the issuing thread)
                 if (it > 0 && !tc::mbar_wait(&bar[(MODE & 1) ? 2 : 1], (it - 1) & 1)) atomicOr(t.err, 2);
                 fscan_fill<MODE>(sb + OFF_STAGE + (stage ^ 1) * STG_BYTES, f, (size_t)(c + 1) * H + h,
                                  &full[stage ^ 1]);
@@ -605,26 +624,23 @@ __device__ __forceinline__ void fscan_issue(const Shape& s, const Table& t, cons
         }
         __syncwarp();
         tc::named_sync(NB_AR, ST_ALL);
-        if (lane == 0) {
-            tc::fence_after_sync();
-            // S^T += R^T F first (it gates the next chunk), then O^T = S^T Q_g^T + R^T C_q^T
-#pragma unroll 1
-            for (int ks = 0; ks < 4; ++ks)
-                tc::mma_bf16(tb, tc::sdesc_k(aR, D, ks), tc::sdesc_mn(stg + STG_KG, BT * 128, ks),
-                             tc::idesc_bf16_bmn(128, 128), 1);
-            tc::mma_commit(&bar[1]);
-            if (MODE & 1) {
-                const uint32_t tO = tb + T_O + 64 * stage, id = tc::idesc_bf16(128, 64);
-#pragma unroll 1
-                for (int ks = 0; ks < 8; ++ks)
-                    tc::mma_bf16(tO, tc::sdesc_k(aS, D, ks), tc::sdesc_k(stg + STG_QG, BT, ks), id, ks > 0);
-#pragma unroll 1
-                for (int ks = 0; ks < 4; ++ks)
-                    tc::mma_bf16(tO, tc::sdesc_k(aR, D, ks), tc::sdesc_k(stg + STG_AQ, BT, ks), id, 1);
-                tc::mma_commit(&bar[2]);
-            }
+        tc::fence_after_sync();
+        // S^T += R^T F first (it gates the next chunk), then O^T = S^T Q_g^T + R^T C_q^T
+        {
+            const uint64_t dF = tc::sdesc_mn(stg + STG_KG, BT * 128, 0);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) tc::mma_bf16_ts_w(tb, aR + 8 * ks, tc::kstep_mn(dF, ks), i128m, 1);
+            tc::mma_commit_w(&bar[1]);
         }
-        __syncwarp();
+        if (MODE & 1) {
+            const uint32_t tO = tb + T_O + 64 * stage;
+            const uint64_t dQ = tc::sdesc(stg + STG_QG), dA = tc::sdesc(stg + STG_AQ);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) tc::mma_bf16_ts_w(tO, aS + 8 * ks, tc::kstep_k(dQ, BT, ks), i64, ks > 0);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) tc::mma_bf16_ts_w(tO, aR + 8 * ks, tc::kstep_k(dA, BT, ks), i64, 1);
+            tc::mma_commit_w(&bar[2]);
+        }
     }
 }
 

@@ -175,6 +175,14 @@ __device__ __forceinline__ void tmem_ld16(uint32_t a, float (&v)[16]) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
+__device__ __forceinline__ void tmem_st16u(uint32_t a, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(a),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
 __device__ __forceinline__ void tmem_st16(uint32_t a, const float (&v)[16]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
@@ -214,6 +222,39 @@ __device__ __forceinline__ void mma_tf32_ts(uint32_t d, uint32_t a, uint64_t b, 
         "r"(a), "l"(b), "r"(idesc), "r"(acc)
         : "memory");
 }
+// Warp-wide forms: every lane of the warp executes them with the same
+// (warp-uniform) operands and the elected leader lane issues, so the
+// descriptors stay in uniform registers. Commits must come from the same
+// warp, which elects the same leader while all lanes are active.
+__device__ __forceinline__ void mma_bf16_w(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+// A from TMEM: M = 128 lanes (row i in lane i), K along columns with two bf16
+// per 32-bit column (lower half = lower k); k-step s starts at column a + 8 s.
+__device__ __forceinline__ void mma_bf16_ts_w(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+        "r"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit_w(uint64_t* bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
+        : "memory");
+}
+// Descriptor of k-step s from the descriptor of k-step 0 (the start address
+// field holds address / 16; shared-memory addresses stay below 2^18).
+__device__ __forceinline__ uint64_t kstep_k(uint64_t d0, int R, int s) {
+    return d0 + (uint64_t)(((s >> 2) * R * 128 + (s & 3) * 32) >> 4);
+}
+__device__ __forceinline__ uint64_t kstep_mn(uint64_t d0, int s) { return d0 + (uint64_t)(s * 2048 >> 4); }
+
 // Completion of all previously issued MMAs of this thread arrives once on bar.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
