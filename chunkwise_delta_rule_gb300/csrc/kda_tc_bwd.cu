@@ -60,13 +60,13 @@ __device__ __forceinline__ void load_tile(uint32_t sbase, const bf16* src, size_
 }
 
 // ====================================================== k_bwd_scan_tc
-constexpr int ST = 256;         // 8 warps: warps w and w+4 share lane quarter w%4, split columns
-constexpr int B_ASB = 0;        // S+bar^T bf16 [128][128] 32 KB
-constexpr int B_ADO = 32768;    // dO^T    bf16 [128][64]  16 KB
-constexpr int B_ARB = 49152;    // R_bar^T bf16 [128][64]  16 KB
-constexpr int B_ANR = 65536;    // -R_bar^T                16 KB
-constexpr int B_STAGE = 81920;  // two stages of B operands
-// B operands in their natural [token][.] layouts: F read K-major, the rest MN-major
+constexpr int ST = 256;            // compute warps: warps w and w+4 share lane quarter w%4, split columns
+constexpr int ST_ALL = ST + 32;    // + one warp that issues the MMAs and the bulk fills
+constexpr int NB_AS = 1;           // named barriers (compute warps + issuer): A operands of R_bar staged
+constexpr int NB_AR = 2;           //   A operands of the state adjoint update and P staged
+constexpr int NB_C = 3;            //   compute warps only
+// B operands as tile images: F read K-major, the rest MN-major
+constexpr int B_STAGE = 0;      // two stages of B operands
 constexpr int S_KG = 0;         // F   [64][128] 16 KB
 constexpr int S_AQ = 16384;     // C_q [64][64]   8 KB
 constexpr int S_AI = 24576;     // A   [64][64]   8 KB
@@ -77,6 +77,10 @@ constexpr int B_LAM = B_STAGE + 2 * B_STG;     // lambda [128] fp32
 constexpr int B_TST = B_LAM + 512;             // per-warp transpose staging, 8 x 1280 B
 constexpr int B_BAR = B_TST + 8 * 1280;
 constexpr int BSCAN_SMEM = B_BAR + 64 + 1024;
+// TMEM columns: S_bar^T fp32 [0,128), R_bar^T fp32 [128,192), P^T double buffer [192,320);
+// bf16 A operands (two values per column): S+bar^T [320,384), R_bar^T [384,416),
+// -R_bar^T [416,448), dO^T [448,480)
+constexpr int T_RB = 128, T_P = 192, T_AS = 320, T_AR = 384, T_NR = 416, T_DO = 448;
 
 // Stages the operand tiles of one chunk (stored as tile images) with bulk
 // copies; one thread; completion arrives on `full` as transaction bytes.
@@ -90,39 +94,33 @@ __device__ __forceinline__ void bscan_fill(uint32_t stg, const FwdTC& f, size_t 
     tc::bulk_g2s(stg + S_W, f.W + ch * BT * D, TILE, full);
 }
 
-__global__ void __launch_bounds__(ST, 1)
-    k_bwd_scan_tc(Shape s, const bf16* __restrict__ dout, const float* __restrict__ dht, Table t, FwdTC f,
-                  BwdTC b, float* __restrict__ dh0) {
-    extern __shared__ unsigned char smem_raw[];
-    unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                           ~static_cast<uintptr_t>(1023));
-    float* sLam = reinterpret_cast<float*>(base + B_LAM);
-    uint64_t* bar = reinterpret_cast<uint64_t*>(base + B_BAR);   // three MMA groups
-    uint64_t* full = bar + 3;                                      // operand stages 0, 1
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 5);
-    const uint32_t sb = tc::smem_u32(base);
-    const int nseq = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+// This thread's half of the dO column of a chunk as packed bf16 pairs (the
+// order of a TMEM A operand row), rows past the chunk end zero.
+__device__ __forceinline__ void bscan_load_do(const bf16* __restrict__ dout, int len, int tok0, int H, int h,
+                                              int ib, int vcol, uint32_t (&pw)[16]) {
+    const uint16_t* src = reinterpret_cast<const uint16_t*>(dout) + ((size_t)(tok0 + ib) * H + h) * D + vcol;
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+        const uint32_t x0 = (ib + i < len) ? src[(size_t)i * H * D] : 0u;
+        const uint32_t x1 = (ib + i + 1 < len) ? src[(size_t)(i + 1) * H * D] : 0u;
+        pw[i / 2] = x0 | (x1 << 16);
+    }
+}
+
+// Compute warps: per chunk (last to first) S+bar^T and dO^T -> bf16 A operands,
+// then (while R_bar runs) S+bar to HBM, S_bar^T <- S+bar^T diag(lambda), P of
+// the previous chunk to HBM, dO of the next chunk; then R_bar^T -> bf16.
+__device__ __forceinline__ void bscan_compute(const Shape& s, const bf16* __restrict__ dout,
+                                              const float* __restrict__ dht, const Table& t, const FwdTC& f,
+                                              const BwdTC& b, float* __restrict__ dh0, unsigned char* base,
+                                              uint64_t* bar, uint32_t tb, int nseq, int h, int c0, int c1) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = warp & 3, half = warp >> 2;
+    float* sLam = reinterpret_cast<float*>(base + B_LAM);
     bf16* tst = reinterpret_cast<bf16*>(base + B_TST + warp * 1280);
     const int H = s.H;
     const int vcol = 32 * quad + lane;
     const int kb = 64 * half, ib = 32 * half;
-    const int c0 = t.seq_chunk0[nseq], c1 = t.seq_chunk0[nseq + 1];
-
-    if (tid == 0) {
-        for (int i = 0; i < 5; ++i) tc::mbar_init(&bar[i], 1);
-        tc::fence_mbar_init();
-        if (c0 < c1) bscan_fill(sb + B_STAGE, f, (size_t)(c1 - 1) * H + h, &full[0]);
-    }
-    int filled = c0 < c1 ? 1 : 0, waited = 0;   // bulk fills issued / consumed (thread 0)
-    if (warp == 0) {
-        tc::tmem_alloc(tslot, 256);
-        tc::tmem_relinquish();
-    }
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-    const uint32_t tb = *tslot;
     const uint32_t tl = tc::taddr(tb, 32 * quad, 0);
     const size_t st_off = ((size_t)nseq * H + h) * D * D;
 
@@ -135,139 +133,115 @@ __global__ void __launch_bounds__(ST, 1)
     }
     tc::tmem_wait_st();
 
-    // this thread's half of the dO column of a chunk, as packed bf16 pairs (loads issued early)
-    auto load_do = [&](int cc, uint32_t (&pw)[16]) {
-        const int len = t.chunk_len[cc], tok0 = t.chunk_tok0[cc];
-        const uint16_t* src = reinterpret_cast<const uint16_t*>(dout) + ((size_t)(tok0 + ib) * H + h) * D + vcol;
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-            const uint32_t x0 = (ib + i < len) ? src[(size_t)i * H * D] : 0u;
-            const uint32_t x1 = (ib + i + 1 < len) ? src[(size_t)(i + 1) * H * D] : 0u;
-            pw[i / 2] = x0 | (x1 << 16);
+    bool ok = true;
+    auto wait_one = [&](uint64_t* bb, uint32_t parity) {
+        if (ok && !tc::mbar_wait(bb, parity)) {
+            ok = false;
+            atomicOr(t.err, 2);
         }
+        tc::fence_after_sync();
     };
     uint32_t dnext[16];
-    if (c0 < c1) load_do(c1 - 1, dnext);
-
-    uint32_t ph0 = 0, ph1 = 0, ph2 = 0;
-    bool ok = true;
-    for (int c = c1 - 1; c >= c0 && ok; --c) {
-        const int it = c1 - 1 - c, stage = it & 1;
+    float gln = 0.f;
+    int lenn = 0, tok0n = 0, cp = -1;   // cp: the previous (later) chunk, whose P is pending
+    if (c0 < c1) {
+        lenn = t.chunk_len[c1 - 1];
+        tok0n = t.chunk_tok0[c1 - 1];
+        if (tid < D) gln = f.GL[((size_t)(c1 - 1) * H + h) * D + tid];
+        bscan_load_do(dout, lenn, tok0n, H, h, ib, vcol, dnext);
+    }
+    for (int c = c1 - 1; c >= c0; --c) {
+        const int it = c1 - 1 - c;
         const size_t ch = (size_t)c * H + h;
-        const uint32_t stg = sb + B_STAGE + stage * B_STG;
-        if (tid < D) sLam[tid] = exp2f(f.GL[ch * D + tid]);
-        // dO^T row of this value column (loaded during the previous chunk)
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-            *reinterpret_cast<uint4*>(base + B_ADO + tc::sw128_off(D, vcol, ib * 2 + q * 16)) =
-                make_uint4(dnext[4 * q], dnext[4 * q + 1], dnext[4 * q + 2], dnext[4 * q + 3]);
-        __syncthreads();
-        // S+bar^T -> bf16 operand and HBM; then S_bar^T <- S+bar^T diag(lambda)
-        bf16* SBP = b.SBP + ch * D * D;
+        if (tid < D) sLam[tid] = exp2f(gln);
+        int lenm = 0, tok0m = 0;
+        if (c - 1 >= c0) {
+            lenm = t.chunk_len[c - 1];
+            tok0m = t.chunk_tok0[c - 1];
+            if (tid < D) gln = f.GL[(ch - H) * D + tid];
+        }
+        if (it > 0) wait_one(&bar[1], (it - 1) & 1);   // state adjoint update of the later chunk
+        tc::named_sync(NB_C, ST);
+        // 1. S+bar^T and dO^T -> bf16 A operands in TMEM, handed to the issuer
         float sv[4][16];
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) tc::tmem_ld16(tl + kb + 16 * q4, sv[q4]);
         tc::tmem_wait_ld();
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-            const int cb = kb + 16 * q4;
-            float (&a)[16] = sv[q4];
-            uint32_t pw[8];
-#pragma unroll
-            for (int jj = 0; jj < 8; ++jj) pw[jj] = tc::pack_bf16(a[2 * jj], a[2 * jj + 1]);
-            *reinterpret_cast<uint4*>(base + B_ASB + tc::sw128_off(D, vcol, cb * 2)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
-            *reinterpret_cast<uint4*>(base + B_ASB + tc::sw128_off(D, vcol, cb * 2 + 16)) = make_uint4(pw[4], pw[5], pw[6], pw[7]);
-            tc::warp_store_t16(tst, a, SBP + (size_t)cb * D + 32 * quad, D, 16, lane);
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj) a[jj] *= sLam[cb + jj];
-            tc::tmem_st16(tl + cb, a);
-        }
-        tc::tmem_wait_st();
-        tc::fence_async_smem();
-        tc::fence_before_sync();
-        __syncthreads();
-        if (tid == 0) {
-            tc::fence_after_sync();
-            if (!tc::mbar_wait(&full[stage], (it >> 1) & 1)) atomicOr(t.err, 2);
-            ++waited;
-            const uint32_t i64 = tc::idesc_bf16(128, 64);
-            const uint32_t m64 = tc::idesc_bf16_bmn(128, 64), m128 = tc::idesc_bf16_bmn(128, 128);
-#pragma unroll 1
-            for (int ks = 0; ks < 8; ++ks)
-                tc::mma_bf16(tb + 128, tc::sdesc_k(sb + B_ASB, D, ks), tc::sdesc_k(stg + S_KG, BT, ks), i64, ks > 0);
-#pragma unroll 1
-            for (int ks = 0; ks < 4; ++ks)
-                tc::mma_bf16(tb + 128, tc::sdesc_k(sb + B_ADO, D, ks), tc::sdesc_mn(stg + S_AQ, BT * 128, ks), m64, 1);
-            tc::mma_commit(&bar[0]);
-#pragma unroll 1
-            for (int ks = 0; ks < 4; ++ks)
-                tc::mma_bf16(tb, tc::sdesc_k(sb + B_ADO, D, ks), tc::sdesc_mn(stg + S_QG, BT * 128, ks), m128, 1);
-        }
-        if (c - 1 >= c0 && tid == 0) {
-            bscan_fill(sb + B_STAGE + (stage ^ 1) * B_STG, f, (size_t)(c - 1) * H + h, &full[stage ^ 1]);
-            ++filled;
-        }
-        ok = wait_all(&bar[0], ph0, t.err);
-        ph0 ^= 1;
-        if (!ok) break;
-        tc::fence_after_sync();
-        // R_bar^T -> bf16 operands (and its negation), this thread's half of the rows
-        float rv[2][16];
-        tc::tmem_ld16(tl + 128 + ib, rv[0]);
-        tc::tmem_ld16(tl + 128 + ib + 16, rv[1]);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int cq = 0; cq < 32; cq += 16) {
-            float (&a)[16] = rv[cq / 16];
-            uint32_t pw[8], nw[8];
+        for (int hq = 0; hq < 2; ++hq) {
+            uint32_t pw[16];
 #pragma unroll
             for (int jj = 0; jj < 8; ++jj) {
-                pw[jj] = tc::pack_bf16(a[2 * jj], a[2 * jj + 1]);
-                nw[jj] = tc::pack_bf16(-a[2 * jj], -a[2 * jj + 1]);
+                pw[jj] = tc::pack_bf16(sv[2 * hq][2 * jj], sv[2 * hq][2 * jj + 1]);
+                pw[8 + jj] = tc::pack_bf16(sv[2 * hq + 1][2 * jj], sv[2 * hq + 1][2 * jj + 1]);
             }
-            const int bo = (ib + cq) * 2;
-            *reinterpret_cast<uint4*>(base + B_ARB + tc::sw128_off(D, vcol, bo)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
-            *reinterpret_cast<uint4*>(base + B_ARB + tc::sw128_off(D, vcol, bo + 16)) = make_uint4(pw[4], pw[5], pw[6], pw[7]);
-            *reinterpret_cast<uint4*>(base + B_ANR + tc::sw128_off(D, vcol, bo)) = make_uint4(nw[0], nw[1], nw[2], nw[3]);
-            *reinterpret_cast<uint4*>(base + B_ANR + tc::sw128_off(D, vcol, bo + 16)) = make_uint4(nw[4], nw[5], nw[6], nw[7]);
+            tc::tmem_st16u(tl + T_AS + kb / 2 + 16 * hq, pw);
         }
-        tc::fence_async_smem();
+        tc::tmem_st16u(tl + T_DO + ib / 2, dnext);
+        tc::tmem_wait_st();
         tc::fence_before_sync();
-        __syncthreads();
-        if (tid == 0) {
-            tc::fence_after_sync();
-            const uint32_t m64 = tc::idesc_bf16_bmn(128, 64), m128 = tc::idesc_bf16_bmn(128, 128);
-#pragma unroll 1
-            for (int ks = 0; ks < 4; ++ks)
-                tc::mma_bf16(tb + 192, tc::sdesc_k(sb + B_ARB, D, ks), tc::sdesc_mn(stg + S_AI, BT * 128, ks), m64, ks > 0);
-            tc::mma_commit(&bar[2]);
-#pragma unroll 1
-            for (int ks = 0; ks < 4; ++ks)
-                tc::mma_bf16(tb, tc::sdesc_k(sb + B_ANR, D, ks), tc::sdesc_mn(stg + S_W, BT * 128, ks), m128, 1);
-            tc::mma_commit(&bar[1]);
+        tc::named_sync(NB_AS, ST_ALL);
+        // 2. while R_bar runs: S+bar to HBM, S_bar^T <- S+bar^T diag(lambda), P of the later
+        //    chunk, dO of the next chunk
+        bf16* SBP = b.SBP + ch * D * D;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+            const int cb = kb + 16 * q4;
+            tc::warp_store_t16(tst, sv[q4], SBP + (size_t)cb * D + 32 * quad, D, 16, lane);
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) sv[q4][jj] *= sLam[cb + jj];
+            tc::tmem_st16(tl + cb, sv[q4]);
         }
-        if (c - 1 >= c0) load_do(c - 1, dnext);
-        ok = wait_all(&bar[2], ph2, t.err);
-        ph2 ^= 1;
-        if (!ok) break;
-        tc::fence_after_sync();
-        bf16* P = b.P + ch * BT * D;
-        {
+        tc::tmem_wait_st();
+        if (cp >= 0) {
+            wait_one(&bar[2], (it - 1) & 1);
+            bf16* P = b.P + ((size_t)cp * H + h) * BT * D;
             float pv[2][16];
-            tc::tmem_ld16(tl + 192 + ib, pv[0]);
-            tc::tmem_ld16(tl + 192 + ib + 16, pv[1]);
+            const uint32_t tp = tl + T_P + 64 * ((it - 1) & 1);
+            tc::tmem_ld16(tp + ib, pv[0]);
+            tc::tmem_ld16(tp + ib + 16, pv[1]);
             tc::tmem_wait_ld();
             tc::warp_store_t16(tst, pv[0], P + (size_t)ib * D + 32 * quad, D, 16, lane);
             tc::warp_store_t16(tst, pv[1], P + (size_t)(ib + 16) * D + 32 * quad, D, 16, lane);
         }
+        if (c - 1 >= c0) bscan_load_do(dout, lenm, tok0m, H, h, ib, vcol, dnext);
+        // 3. R_bar^T -> bf16 A operands R_bar^T and -R_bar^T, handed over
+        wait_one(&bar[0], it & 1);
+        {
+            float rv[2][16];
+            tc::tmem_ld16(tl + T_RB + ib, rv[0]);
+            tc::tmem_ld16(tl + T_RB + ib + 16, rv[1]);
+            tc::tmem_wait_ld();
+            uint32_t pw[16], nw[16];
+#pragma unroll
+            for (int cq = 0; cq < 2; ++cq)
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) {
+                    pw[8 * cq + jj] = tc::pack_bf16(rv[cq][2 * jj], rv[cq][2 * jj + 1]);
+                    nw[8 * cq + jj] = tc::pack_bf16(-rv[cq][2 * jj], -rv[cq][2 * jj + 1]);
+                }
+            tc::tmem_st16u(tl + T_AR + ib / 2, pw);
+            tc::tmem_st16u(tl + T_NR + ib / 2, nw);
+        }
+        tc::tmem_wait_st();
         tc::fence_before_sync();
-        ok = wait_all(&bar[1], ph1, t.err);
-        ph1 ^= 1;
-        if (!ok) break;
-        tc::fence_after_sync();
+        tc::named_sync(NB_AR, ST_ALL);
+        cp = c;
+    }
+    if (c1 > c0) {
+        const int last = c1 - 1 - c0;
+        wait_one(&bar[1], last & 1);
+        wait_one(&bar[2], last & 1);
+        bf16* P = b.P + ((size_t)c0 * H + h) * BT * D;
+        float pv[2][16];
+        const uint32_t tp = tl + T_P + 64 * (last & 1);
+        tc::tmem_ld16(tp + ib, pv[0]);
+        tc::tmem_ld16(tp + ib + 16, pv[1]);
+        tc::tmem_wait_ld();
+        tc::warp_store_t16(tst, pv[0], P + (size_t)ib * D + 32 * quad, D, 16, lane);
+        tc::warp_store_t16(tst, pv[1], P + (size_t)(ib + 16) * D + 32 * quad, D, 16, lane);
     }
     if (ok && dh0) {
-        tc::fence_after_sync();
 #pragma unroll 1
         for (int cb = kb; cb < kb + 64; cb += 16) {
             float a[16];
@@ -277,12 +251,104 @@ __global__ void __launch_bounds__(ST, 1)
             for (int jj = 0; jj < 16; ++jj) dh0[st_off + (size_t)(cb + jj) * D + vcol] = a[jj];
         }
     }
-    // after an early exit, let a bulk fill still in flight land before the CTA leaves
-    if (tid == 0)
+}
+
+// Issuer warp: bulk fills (lane 0) and the three MMA groups of every chunk
+// (warp-uniform descriptors, one elected lane issuing).
+__device__ __forceinline__ void bscan_issue(const Shape& s, const Table& t, const FwdTC& f, uint32_t sb,
+                                            uint64_t* bar, uint64_t* full, uint32_t tb, int h, int c0, int c1,
+                                            int& filled, int& waited) {
+    const int lane = threadIdx.x & 31;
+    const int H = s.H;
+    const uint32_t i64 = tc::idesc_bf16(128, 64), m64 = tc::idesc_bf16_bmn(128, 64),
+                   m128 = tc::idesc_bf16_bmn(128, 128);
+    for (int c = c1 - 1; c >= c0; --c) {
+        const int it = c1 - 1 - c, stage = it & 1;
+        const uint32_t stg = sb + B_STAGE + stage * B_STG;
+        tc::named_sync(NB_AS, ST_ALL);
+        tc::fence_after_sync();
+        if (!tc::mbar_wait(&full[stage], (it >> 1) & 1) && lane == 0) atomicOr(t.err, 2);
+        {
+            // R_bar^T = S+bar^T F^T + dO^T C_q
+            const uint64_t dF = tc::sdesc(stg + S_KG), dC = tc::sdesc_mn(stg + S_AQ, BT * 128, 0);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+                tc::mma_bf16_ts_w(tb + T_RB, tb + T_AS + 8 * ks, tc::kstep_k(dF, BT, ks), i64, ks > 0);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                tc::mma_bf16_ts_w(tb + T_RB, tb + T_DO + 8 * ks, tc::kstep_mn(dC, ks), m64, 1);
+            tc::mma_commit_w(&bar[0]);
+        }
+        if (lane == 0) {
+            ++waited;
+            if (c - 1 >= c0) {
+                // the other stage is free once every MMA of the later chunk has completed
+                if (it > 0 && !tc::mbar_wait(&bar[2], (it - 1) & 1)) atomicOr(t.err, 2);
+                bscan_fill(sb + B_STAGE + (stage ^ 1) * B_STG, f, (size_t)(c - 1) * H + h, &full[stage ^ 1]);
+                ++filled;
+            }
+        }
+        __syncwarp();
+        tc::named_sync(NB_AR, ST_ALL);
+        tc::fence_after_sync();
+        {
+            // S_bar^T += dO^T Q_g - R_bar^T W (it gates the next chunk), then P^T = R_bar^T A
+            const uint64_t dQ = tc::sdesc_mn(stg + S_QG, BT * 128, 0), dW = tc::sdesc_mn(stg + S_W, BT * 128, 0);
+            const uint64_t dA = tc::sdesc_mn(stg + S_AI, BT * 128, 0);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) tc::mma_bf16_ts_w(tb, tb + T_DO + 8 * ks, tc::kstep_mn(dQ, ks), m128, 1);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) tc::mma_bf16_ts_w(tb, tb + T_NR + 8 * ks, tc::kstep_mn(dW, ks), m128, 1);
+            tc::mma_commit_w(&bar[1]);
+            const uint32_t tP = tb + T_P + 64 * stage;
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) tc::mma_bf16_ts_w(tP, tb + T_AR + 8 * ks, tc::kstep_mn(dA, ks), m64, ks > 0);
+            tc::mma_commit_w(&bar[2]);
+        }
+    }
+}
+
+__global__ void __launch_bounds__(ST_ALL, 1)
+    k_bwd_scan_tc(Shape s, const bf16* __restrict__ dout, const float* __restrict__ dht, Table t, FwdTC f,
+                  BwdTC b, float* __restrict__ dh0) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                           ~static_cast<uintptr_t>(1023));
+    uint64_t* bar = reinterpret_cast<uint64_t*>(base + B_BAR);   // R_bar, state adjoint update, P
+    uint64_t* full = bar + 3;                                      // operand stages 0, 1
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 5);
+    const uint32_t sb = tc::smem_u32(base);
+    const int nseq = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5;
+    const int c0 = t.seq_chunk0[nseq], c1 = t.seq_chunk0[nseq + 1];
+    const bool issuer = warp == ST / 32;
+    int filled = 0, waited = 0;   // bulk fills issued / consumed (issuer lane 0)
+
+    if (issuer && (tid & 31) == 0) {
+        for (int i = 0; i < 5; ++i) tc::mbar_init(&bar[i], 1);
+        tc::fence_mbar_init();
+        if (c0 < c1) {
+            bscan_fill(sb + B_STAGE, f, (size_t)(c1 - 1) * s.H + h, &full[0]);
+            filled = 1;
+        }
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(tslot, 512);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tb = *tslot;
+    if (issuer)
+        bscan_issue(s, t, f, sb, bar, full, tb, h, c0, c1, filled, waited);
+    else
+        bscan_compute(s, dout, dht, t, f, b, dh0, base, bar, tb, nseq, h, c0, c1);
+    // a bulk fill still in flight (only after a timeout) lands before the CTA leaves
+    if (issuer && (tid & 31) == 0)
         for (; waited < filled; ++waited) tc::mbar_wait(&full[waited & 1], (waited >> 1) & 1);
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 0) tc::tmem_dealloc(tb, 256);
+    if (warp == 0) tc::tmem_dealloc(tb, 512);
 }
 
 // ================================================== k_bwd_consumer_tc
@@ -760,7 +826,7 @@ cudaError_t launch_bwd_scan_tc(const Shape& s, const void* dout, const float* dh
     cudaError_t e = set_smem_once<k_bwd_scan_tc>(BSCAN_SMEM);
     if (e != cudaSuccess) return e;
     dim3 grid(s.N, s.H);
-    k_bwd_scan_tc<<<grid, ST, BSCAN_SMEM, st>>>(s, (const bf16*)dout, dht, t, f, b, dh0);
+    k_bwd_scan_tc<<<grid, ST_ALL, BSCAN_SMEM, st>>>(s, (const bf16*)dout, dht, t, f, b, dh0);
     return cudaGetLastError();
 }
 
