@@ -493,16 +493,18 @@ __global__ void __launch_bounds__(CT, 1)
     const uint32_t tb = *tslot;
     // TMEM columns: [0,64) [H_q ; -D] -> [H_q ; D] ; [64,192) [dO S^T ; P S^T] ;
     // [192,256) F_bar^T ; [256,384) [T_q ; T_e] ; [384,448) T_y^T
-    if (tid == 0) {
-        // [dO ; P] [R ; S]^T fills columns [0, 192) in one N = 192 pass
+    if (warp == 0) {
+        // [dO ; P] [R ; S]^T fills columns [0, 192) in one N = 192 pass (warp-uniform
+        // descriptors, one elected lane issuing)
         const uint32_t i64 = tc::idesc_bf16(128, 64), i192 = tc::idesc_bf16(128, BT + D);
-#pragma unroll 1
+        const uint64_t dOP = tc::sdesc(sb + X_OP), dRS = tc::sdesc(sb + X_RS), dSB = tc::sdesc(sb + X_SB);
+#pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-            tc::mma_bf16(tb, tc::sdesc_k(sb + X_OP, D, ks), tc::sdesc_k(sb + X_RS, BT + D, ks), i192, ks > 0);
-#pragma unroll 1
+            tc::mma_bf16_w(tb, tc::kstep_k(dOP, D, ks), tc::kstep_k(dRS, BT + D, ks), i192, ks > 0);
+#pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-            tc::mma_bf16(tb + 192, tc::sdesc_k(sb + X_SB, D, ks), tc::sdesc_k(sb + X_RS, BT + D, ks), i64, ks > 0);
-        tc::mma_commit(bar);
+            tc::mma_bf16_w(tb + 192, tc::kstep_k(dSB, D, ks), tc::kstep_k(dRS, BT + D, ks), i64, ks > 0);
+        tc::mma_commit_w(bar);
     }
     // while the MMAs run: cumsum (4 segments of 16 rows per feature), anchors, alpha tile;
     // rowsum(S .* S+bar) and <v_i, P_i>, dv = beta P from the staged tiles
@@ -639,16 +641,17 @@ __global__ void __launch_bounds__(CT, 1)
         tc::fence_async_smem();
         tc::fence_before_sync();
         __syncthreads();
-        if (tid == 0) {
+        if (warp == 0) {
             tc::fence_after_sync();
             const uint32_t i128 = tc::idesc_tf32(128, 128), i64 = tc::idesc_tf32(128, 64);
-#pragma unroll 1
+            const uint64_t dKZ = tc::sdesc(sb + X_KZ), dEQ = tc::sdesc(sb + X_EQ), dDH = tc::sdesc(sb + X_DH);
+#pragma unroll
             for (int ks = 0; ks < 8; ++ks)
-                tc::mma_tf32_ts(tb + 256, tb + 8 * ks, tc::sdesc_k(sb + X_KZ, D, ks), i128, ks > 0);
-#pragma unroll 1
+                tc::mma_tf32_ts_w(tb + 256, tb + 8 * ks, tc::kstep_k(dKZ, D, ks), i128, ks > 0);
+#pragma unroll
             for (int ks = 0; ks < 16; ++ks)
-                tc::mma_tf32(tb + 384, tc::sdesc_k(sb + X_EQ, D, ks), tc::sdesc_k(sb + X_DH, BT, ks), i64, ks > 0);
-            tc::mma_commit(bar);
+                tc::mma_tf32_w(tb + 384, tc::kstep_k(dEQ, D, ks), tc::kstep_k(dDH, BT, ks), i64, ks > 0);
+            tc::mma_commit_w(bar);
         }
         ok = wait_all(bar, 1, t.err);
     }
