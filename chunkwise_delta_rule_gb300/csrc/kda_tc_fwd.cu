@@ -6,8 +6,8 @@
 //       [Akk ; Aqk] = [beta K 2^(G2-c) ; s Q 2^(G2-c)] (K 2^(c-G2))^T
 //   is a single M = 128, N = 64, K = 128 bf16 MMA ("Kimi Delta Attention"
 //   blog, sections 6.3 and 6.5; "ReWY" paper, centered factors); strict /
-//   inclusive masks on the TMEM read-back; A = (I + Akk)^-1 in fp32 by
-//   forward substitution in registers; W^T = (E'^T A^T) diag(2^c) and
+//   inclusive masks on the TMEM read-back; A = (I + Akk)^-1 in fp32, 16 x 16
+//   diagonal blocks by forward substitution and two levels of block merges; W^T = (E'^T A^T) diag(2^c) and
 //   U^T = V^T (A diag(beta))^T as M = 128 bf16 MMAs whose A operands E' =
 //   beta K alpha (already in shared memory for the first MMA) and V are read
 //   MN-major. A chunk whose gate range exceeds 2^80 is left to the CUDA-core
@@ -51,39 +51,94 @@ constexpr int LG = D + 4;   // fp32 row stride of the G2 / alpha tile (16-byte a
 constexpr int LW = D + 8;   // row stride (bf16) of the staged W tile
 
 // A = (I + L)^-1 for the strictly lower 64 x 64 L, given as L^T (fp32, row m
-// holds column m of L), by forward substitution on row vectors,
-//     A_i = e_i - sum_{m<i} L_im A_m,
-// applied right-looking: once row m of A is final it is broadcast and every
-// later row subtracts L_im A_m. Warp w owns the columns 8w..8w+7 (rows of A
-// have zeros left of the diagonal, so the warp starts at pivot 8w), lane l
-// the rows l and l + 32. No block-level synchronisation.
-__device__ __forceinline__ void inverse_rows(const float* sLt, int warp, int lane, float (&x0)[8], float (&x1)[8]) {
-    const int cb = 8 * warp;
+// holds column m of L), into sAi (fp32, row stride LA), blockwise:
+//  1. the four 16 x 16 diagonal blocks by forward substitution on row vectors,
+//     A_i = e_i - sum_{m<i} L_im A_m, applied right-looking (warp b owns block
+//     b; lane l holds row l % 16, half l / 16 of the columns);
+//  2. the 16 x 16 blocks below them, A_10 = -A_11 (L_10 A_00) (and 3, 2);
+//  3. the lower-left 32 x 32 block the same way from the 32 x 32 halves.
+// Every block row/column product is a plain fp32 sum; 256 threads.
+constexpr int LA = BT + 1;   // row stride of sAi
+constexpr int LT1 = 17, LT2 = 33;
+__device__ __forceinline__ void inverse_blocked(const float* __restrict__ sLt, float* __restrict__ sAi,
+                                                float* __restrict__ sT, int tid, int warp, int lane) {
+    if (warp < 4) {
+        const int b0 = 16 * warp, r = lane & 15, ch = lane >> 4;
+        float x[8];
 #pragma unroll
-    for (int cc = 0; cc < 8; ++cc) {
-        x0[cc] = (lane == cb + cc) ? 1.f : 0.f;
-        x1[cc] = (lane + 32 == cb + cc) ? 1.f : 0.f;
-    }
+        for (int cc = 0; cc < 8; ++cc) x[cc] = (r == 8 * ch + cc) ? 1.f : 0.f;
 #pragma unroll 1
-    for (int m = cb; m < 32; ++m) {
-        const float l0 = sLt[m * BT + lane], l1 = sLt[m * BT + 32 + lane];
+        for (int m = 0; m < 15; ++m) {
+            const float l = sLt[(b0 + m) * BT + b0 + r];   // L[b0 + r][b0 + m]
 #pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-            const float p = __shfl_sync(0xffffffffu, x0[cc], m);
-            x0[cc] = fmaf(-l0, p, x0[cc]);
-            x1[cc] = fmaf(-l1, p, x1[cc]);
+            for (int cc = 0; cc < 8; ++cc) x[cc] = fmaf(-l, __shfl_sync(0xffffffffu, x[cc], (lane & 16) | m), x[cc]);
+        }
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) sAi[(b0 + r) * LA + b0 + 8 * ch + cc] = x[cc];
+    } else {
+        // zero blocks above the diagonal
+        for (int idx = tid - 128; idx < 6 * 256; idx += 128) {
+            const int blk = idx >> 8, e = idx & 255;
+            const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+            const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+            sAi[(16 * bi + (e >> 4)) * LA + 16 * bj + (e & 15)] = 0.f;
         }
     }
-    // pivots 32..62 touch only the rows l + 32 (L_lm = 0 for l < 32 <= m)
-#pragma unroll 1
-    for (int m = (cb > 32 ? cb : 32); m < BT - 1; ++m) {
-        const float l1 = sLt[m * BT + 32 + lane];
+    __syncthreads();
+    {   // T = L_10 A_00 (pair 0) and L_32 A_22 (pair 1); two outputs per thread
+        const int pr = tid >> 7, r = (tid >> 3) & 15, c = (tid & 7) * 2;
+        const int bi = 32 * pr + 16, bj = 32 * pr;
+        float t0 = 0.f, t1 = 0.f;
 #pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-            const float p = __shfl_sync(0xffffffffu, x1[cc], m - 32);
-            x1[cc] = fmaf(-l1, p, x1[cc]);
+        for (int k = 0; k < 16; ++k) {
+            const float l = sLt[(bj + k) * BT + bi + r];
+            t0 = fmaf(l, sAi[(bj + k) * LA + bj + c], t0);
+            t1 = fmaf(l, sAi[(bj + k) * LA + bj + c + 1], t1);
         }
+        sT[(16 * pr + r) * LT1 + c] = t0;
+        sT[(16 * pr + r) * LT1 + c + 1] = t1;
     }
+    __syncthreads();
+    {   // A_10 = -A_11 T
+        const int pr = tid >> 7, r = (tid >> 3) & 15, c = (tid & 7) * 2;
+        const int bi = 32 * pr + 16, bj = 32 * pr;
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const float x = sAi[(bi + r) * LA + bi + k];
+            a0 = fmaf(x, sT[(16 * pr + k) * LT1 + c], a0);
+            a1 = fmaf(x, sT[(16 * pr + k) * LT1 + c + 1], a1);
+        }
+        sAi[(bi + r) * LA + bj + c] = -a0;
+        sAi[(bi + r) * LA + bj + c + 1] = -a1;
+    }
+    __syncthreads();
+    {   // T = L[32:64][0:32] A[0:32][0:32]; four outputs per thread
+        const int r = tid >> 3, c = (tid & 7) * 4;
+        float t[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+        for (int k = 0; k < 32; ++k) {
+            const float l = sLt[k * BT + 32 + r];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) t[e] = fmaf(l, sAi[k * LA + c + e], t[e]);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sT[r * LT2 + c + e] = t[e];
+    }
+    __syncthreads();
+    {   // A[32:64][0:32] = -A[32:64][32:64] T
+        const int r = tid >> 3, c = (tid & 7) * 4;
+        float a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+        for (int k = 0; k < 32; ++k) {
+            const float x = sAi[(32 + r) * LA + 32 + k];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) a[e] = fmaf(x, sT[k * LT2 + c + e], a[e]);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sAi[(32 + r) * LA + c + e] = -a[e];
+    }
+    __syncthreads();
 }
 
 // Shared-memory map of k_prep_tc (bytes from the 1024-aligned base); regions
@@ -97,10 +152,13 @@ constexpr int P_V = 49152;         // V bf16 [64][128] (MN-major view for U^T)  
 constexpr int P_ALPHA = 65536;     // G2, then alpha = 2^(G2 - c), fp32 [64][LG]            33 KB
 constexpr int P_BA = 65536;        //   after MMA 1: A bf16 [64][64], K-major                 8 KB
 constexpr int P_BB = 65536 + 8192; //                A diag(beta) bf16 [64][64], K-major      8 KB
+constexpr int P_AIF = 65536 + 16384;  //              A fp32 [64][LA] (the blocked inverse)  16.3 KB
+constexpr int P_TMP = 8192;        //   after MMA 1 (rows 64..127 of A1's first atom): products  4.2 KB
 constexpr int P_MISC = P_ALPHA + 4 * BT * LG;  // beta [64], 2^c [128], 2^(G2_last - c) [128]
 constexpr int P_BAR = P_MISC + 4 * (BT + 2 * D);
 constexpr size_t PREP_SMEM = P_BAR + 64 + 1024;
-static_assert(P_BB + 8192 <= P_MISC, "A tiles overlap the constants");
+static_assert(P_AIF + 4 * BT * LA <= P_MISC, "A tiles overlap the constants");
+static_assert(P_TMP + 4 * 32 * LT2 <= 16384, "inverse scratch overlaps E'");
 static_assert(BT * LW * 2 <= P_B1, "W staging overlaps L^T");
 
 template <int GATE, bool BWD>
@@ -303,32 +361,24 @@ __global__ void __launch_bounds__(PT, 2)
             }
         }
         __syncthreads();
-        // a3 + a4: A = (I + Akk)^-1 in registers, then the bf16 B operands A (for W^T = E'^T A^T)
-        // and A diag(beta) (for U^T = V^T (A diag(beta))^T), and A itself for the backward
-        {
-            float x0[8], x1[8];
-            inverse_rows(sLt, warp, lane, x0, x1);
-            const int cb = 8 * warp;
-            float bj[8];
-            *reinterpret_cast<float4*>(bj) = *reinterpret_cast<const float4*>(sBeta + cb);
-            *reinterpret_cast<float4*>(bj + 4) = *reinterpret_cast<const float4*>(sBeta + cb + 4);
-            uint32_t a0[4], a1[4], b0[4], b1[4];
+        // a3 + a4: A = (I + Akk)^-1, then the bf16 B operands A (for W^T = E'^T A^T) and
+        // A diag(beta) (for U^T = V^T (A diag(beta))^T), and A itself for the backward
+        float* sAi = reinterpret_cast<float*>(base + P_AIF);
+        inverse_blocked(sLt, sAi, reinterpret_cast<float*>(base + P_TMP), tid, warp, lane);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const int i = tid >> 2, c8 = 16 * (tid & 3) + 8 * hh;
+            const float* ai = sAi + i * LA + c8;
+            uint32_t a[4], bb[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                a0[e] = tc::pack_bf16(x0[2 * e], x0[2 * e + 1]);
-                a1[e] = tc::pack_bf16(x1[2 * e], x1[2 * e + 1]);
-                b0[e] = tc::pack_bf16(x0[2 * e] * bj[2 * e], x0[2 * e + 1] * bj[2 * e + 1]);
-                b1[e] = tc::pack_bf16(x1[2 * e] * bj[2 * e], x1[2 * e + 1] * bj[2 * e + 1]);
+                a[e] = tc::pack_bf16(ai[2 * e], ai[2 * e + 1]);
+                bb[e] = tc::pack_bf16(ai[2 * e] * sBeta[c8 + 2 * e], ai[2 * e + 1] * sBeta[c8 + 2 * e + 1]);
             }
-            const uint4 va0 = make_uint4(a0[0], a0[1], a0[2], a0[3]), va1 = make_uint4(a1[0], a1[1], a1[2], a1[3]);
-            *reinterpret_cast<uint4*>(base + P_BA + tc::sw128_off(BT, lane, 2 * cb)) = va0;
-            *reinterpret_cast<uint4*>(base + P_BA + tc::sw128_off(BT, lane + 32, 2 * cb)) = va1;
-            *reinterpret_cast<uint4*>(base + P_BB + tc::sw128_off(BT, lane, 2 * cb)) = make_uint4(b0[0], b0[1], b0[2], b0[3]);
-            *reinterpret_cast<uint4*>(base + P_BB + tc::sw128_off(BT, lane + 32, 2 * cb)) = make_uint4(b1[0], b1[1], b1[2], b1[3]);
-            if (BWD) {
-                *reinterpret_cast<uint4*>(f.AI + ch * BT * BT + tile_el(BT, lane, cb)) = va0;
-                *reinterpret_cast<uint4*>(f.AI + ch * BT * BT + tile_el(BT, lane + 32, cb)) = va1;
-            }
+            const uint4 va = make_uint4(a[0], a[1], a[2], a[3]);
+            *reinterpret_cast<uint4*>(base + P_BA + tc::sw128_off(BT, i, 2 * c8)) = va;
+            *reinterpret_cast<uint4*>(base + P_BB + tc::sw128_off(BT, i, 2 * c8)) = make_uint4(bb[0], bb[1], bb[2], bb[3]);
+            if (BWD) *reinterpret_cast<uint4*>(f.AI + ch * BT * BT + tile_el(BT, i, c8)) = va;
         }
         tc::fence_async_smem();
         tc::fence_before_sync();
