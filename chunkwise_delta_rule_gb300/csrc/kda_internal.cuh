@@ -1,6 +1,7 @@
 // Internal declarations shared by the CUDA translation units of libkda.so.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -18,7 +19,6 @@ constexpr float CENTER_RANGE_LOG2 = 80.0f;
 
 constexpr float LOG2E = 1.4426950408889634f;
 
-// Chunk bookkeeping built on the device from cu_seqlens (or from B, T).
 // The bf16 tensor-core intermediates (W, F, Q_g, C_q, A) are stored in HBM as
 // images of their shared-memory operand tiles: a [R][C] tile (C = 64 or 128)
 // in the K-major 128-byte swizzle layout (64-column atom blocks of R rows of
@@ -28,6 +28,14 @@ __host__ __device__ __forceinline__ int tile_el(int R, int r, int col) {
     return ((col >> 6) * R + r) * 64 + ((((col >> 3) & 7) ^ (r & 7)) << 3) + (col & 7);
 }
 
+// TMA tensor maps of a token-major input [Ttot][H][D] whose boxes are one
+// head's 64-token chunk rows: bf16 in two 64-column boxes with the 128-byte
+// swizzle (each lands as one atom column of a K-major operand tile), fp32 in
+// one unswizzled [64][D] box. False if the map cannot be encoded.
+bool tmap_rows_bf16(CUtensorMap* m, const void* base, int Ttot, int H, int D);
+bool tmap_rows_f32(CUtensorMap* m, const void* base, int Ttot, int H, int D);
+
+// Chunk bookkeeping built on the device from cu_seqlens (or from B, T).
 struct Table {
     int32_t* chunk_tok0;  // [NC] first token of the chunk (packed axis)
     int32_t* chunk_len;   // [NC] tokens in the chunk; 0 marks an unused slot

@@ -25,6 +25,8 @@
 // Attention" blog, section 6.4). The operand tiles of chunk c+1 (stored as
 // tile images) are fetched with bulk copies while chunk c computes; F is read
 // as an MN-major operand.
+#include <string.h>
+
 #include "kda_internal.cuh"
 #include "tc.cuh"
 
@@ -47,7 +49,7 @@ __device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, int32_t
 
 // =========================================================== k_prep_tc
 constexpr int PT = 256;     // 8 warps; ~100 KB of shared memory, so two CTAs share an SM
-constexpr int LG = D + 4;   // fp32 row stride of the G2 / alpha tile (16-byte aligned rows)
+constexpr int LG = D;       // fp32 row stride of the G / alpha tile (dense rows, as TMA lands them)
 constexpr int LW = D + 8;   // row stride (bf16) of the staged W tile
 
 // A = (I + L)^-1 for the strictly lower 64 x 64 L, given as L^T (fp32, row m
@@ -144,37 +146,40 @@ __device__ __forceinline__ void inverse_blocked(const float* __restrict__ sLt, f
 // Shared-memory map of k_prep_tc (bytes from the 1024-aligned base); regions
 // are reused once the MMA that reads them has completed.
 constexpr int P_A1 = 0;            // [beta K alpha ; s Q alpha] bf16 [128][128], K-major    32 KB
+                                   //   (rows 64..127 first hold q as loaded)
                                    //   rows 0..63 double as E' (MN-major view) for W^T
 constexpr int P_W = 0;             //   after MMA 2: W staged bf16 [64][LW]
-constexpr int P_B1 = 32768;        // K / alpha bf16 [64][128], K-major                      16 KB
+constexpr int P_B1 = 32768;        // K / alpha bf16 [64][128], K-major (first k as loaded)  16 KB
 constexpr int P_LT = 32768;        //   after MMA 1: L^T fp32 [64][64]                        16 KB
 constexpr int P_V = 49152;         // V bf16 [64][128] (MN-major view for U^T)              16 KB
-constexpr int P_ALPHA = 65536;     // G2, then alpha = 2^(G2 - c), fp32 [64][LG]            33 KB
+constexpr int P_ALPHA = 65536;     // g, then alpha = 2^(G2 - c), fp32 [64][LG]              32 KB
 constexpr int P_BA = 65536;        //   after MMA 1: A bf16 [64][64], K-major                 8 KB
 constexpr int P_BB = 65536 + 8192; //                A diag(beta) bf16 [64][64], K-major      8 KB
 constexpr int P_AIF = 65536 + 16384;  //              A fp32 [64][LA] (the blocked inverse)  16.3 KB
 constexpr int P_TMP = 8192;        //   after MMA 1 (rows 64..127 of A1's first atom): products  4.2 KB
-constexpr int P_MISC = P_ALPHA + 4 * BT * LG;  // beta [64], 2^c [128], 2^(G2_last - c) [128]
+constexpr int P_MISC = P_AIF + 4 * BT * LA;    // beta [64], 2^c [128], 2^(G2_last - c) [128]
 constexpr int P_BAR = P_MISC + 4 * (BT + 2 * D);
 constexpr size_t PREP_SMEM = P_BAR + 64 + 1024;
-static_assert(P_AIF + 4 * BT * LA <= P_MISC, "A tiles overlap the constants");
+static_assert(P_ALPHA + 4 * BT * LG <= P_MISC, "the G tile overlaps the constants");
 static_assert(P_TMP + 4 * 32 * LT2 <= 16384, "inverse scratch overlaps E'");
 static_assert(BT * LW * 2 <= P_B1, "W staging overlaps L^T");
 
 template <int GATE, bool BWD>
 __global__ void __launch_bounds__(PT, 2)
-    k_prep_tc(Shape s, const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* __restrict__ v,
+    k_prep_tc(Shape s, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+              const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmg,
               const bf16* __restrict__ beta, const float* __restrict__ g, Table t, FwdTC f) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                            ~static_cast<uintptr_t>(1023));
-    float* sA = reinterpret_cast<float*>(base + P_ALPHA);  // G2, then alpha
+    float* sA = reinterpret_cast<float*>(base + P_ALPHA);  // g, then alpha
     float* sBeta = reinterpret_cast<float*>(base + P_MISC);
     float* sC2 = sBeta + BT;   // 2^c
     float* sAL = sC2 + D;      // 2^(G2_last - c)
     float* sLt = reinterpret_cast<float*>(base + P_LT);
-    uint64_t* bar = reinterpret_cast<uint64_t*>(base + P_BAR);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 1);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(base + P_BAR);   // MMA completions
+    uint64_t* bld = bar + 1;                                       // input tiles
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 2);
     const uint32_t sb = tc::smem_u32(base);
 
     const int c = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -186,46 +191,30 @@ __global__ void __launch_bounds__(PT, 2)
     const float scale = s.scale;
     const int c8 = (tid & 15) * 8;   // the 8 feature columns of this thread in every row pass
 
-    // ---- batched vector loads: k, q, v (bf16, 8 per 16 B), g (fp32, 4 per 16 B)
-    constexpr int NU = BT * D / 8 / PT;   // 16-byte bf16 chunks per thread
-    constexpr int NG = BT * D / 4 / PT;   // 16-byte fp32 chunks per thread
-    uint4 kr4[NU], qr4[NU], vr4[NU];
-#pragma unroll
-    for (int u = 0; u < NU; ++u) {
-        const int r = (tid + PT * u) >> 4;
-        kr4[u] = qr4[u] = vr4[u] = make_uint4(0, 0, 0, 0);
-        if (r < n) {
-            const size_t off = ((size_t)(tok0 + r) * H + h) * D + c8;
-            kr4[u] = __ldg(reinterpret_cast<const uint4*>(k + off));
-            qr4[u] = __ldg(reinterpret_cast<const uint4*>(q + off));
-            vr4[u] = __ldg(reinterpret_cast<const uint4*>(v + off));
-        }
-    }
-    {
-        float4 gr4[NG];
-#pragma unroll
-        for (int u = 0; u < NG; ++u) {
-            const int ci = tid + PT * u, r = ci >> 5, c4 = (ci & 31) * 4;
-            gr4[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (r < n) {
-                if (GATE == 2) gr4[u] = __ldg(reinterpret_cast<const float4*>(g + ((size_t)(tok0 + r) * H + h) * D + c4));
-                if (GATE == 1) {
-                    const float x = __ldg(g + (size_t)(tok0 + r) * H + h);
-                    gr4[u] = make_float4(x, x, x, x);
-                }
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < NG; ++u) {
-            const int ci = tid + PT * u, r = ci >> 5, c4 = (ci & 31) * 4;
-            *reinterpret_cast<float4*>(sA + r * LG + c4) =
-                make_float4(gr4[u].x * LOG2E, gr4[u].y * LOG2E, gr4[u].z * LOG2E, gr4[u].w * LOG2E);
-        }
-    }
-    if (tid < BT) sBeta[tid] = (tid < n) ? bfx(beta + (size_t)(tok0 + tid) * H + h) : 0.f;
+    // ---- inputs by TMA: k -> B1, q -> rows 64..127 of A1, v -> V (SW128 rows, in place for the
+    // MMAs), g -> the G tile (fp32 rows). Rows past the chunk end hold the following tokens (or
+    // zeros past the tensor) and are masked out below.
     if (tid == 0) {
         tc::mbar_init(bar, 1);
+        tc::mbar_init(bld, 1);
         tc::fence_mbar_init();
+        tc::mbar_arrive_expect_tx(bld, 6 * 8192 + (GATE == 2 ? BT * D * 4 : 0));
+        tc::tma_load3(sb + P_B1, &tmk, 0, h, tok0, bld);
+        tc::tma_load3(sb + P_B1 + 8192, &tmk, 64, h, tok0, bld);
+        tc::tma_load3(sb + P_A1 + 8192, &tmq, 0, h, tok0, bld);
+        tc::tma_load3(sb + P_A1 + 24576, &tmq, 64, h, tok0, bld);
+        tc::tma_load3(sb + P_V, &tmv, 0, h, tok0, bld);
+        tc::tma_load3(sb + P_V + 8192, &tmv, 64, h, tok0, bld);
+        if (GATE == 2) tc::tma_load3(sb + P_ALPHA, &tmg, 0, h, tok0, bld);
+    }
+    if (tid < BT) sBeta[tid] = (tid < n) ? bfx(beta + (size_t)(tok0 + tid) * H + h) : 0.f;
+    if (GATE != 2) {
+        // scalar gate: the G tile repeats the token's log-decay; no gate: zeros
+        for (int idx = tid; idx < BT * D / 4; idx += PT) {
+            const int r = idx >> 5, c4 = (idx & 31) * 4;
+            const float x = (GATE == 1 && r < n) ? __ldg(g + (size_t)(tok0 + r) * H + h) : 0.f;
+            *reinterpret_cast<float4*>(sA + r * LG + c4) = make_float4(x, x, x, x);
+        }
     }
     if (warp == 0) {
         tc::tmem_alloc(tslot, 256);
@@ -235,18 +224,21 @@ __global__ void __launch_bounds__(PT, 2)
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tb = *tslot;
+    bool ok = wait_all(bld, 0, t.err);
+    if (!ok && tid == 0) tc::mbar_wait(bld, 0);   // let late tiles land before the CTA can leave
 
     // a1: cumsum by 2 segments of 32 rows per feature (lanes 2c, 2c+1), range, midpoint anchor;
     // alpha = 2^(G2 - c) replaces G2 (one exp2 per element; every decay factor of the chunk is
     // alpha times a per-feature constant or its reciprocal)
     int wide_col = 0;
-    {
+    if (ok) {
         const int col = tid >> 1, seg = tid & 1;
         float x[32];
         float acc = 0.f;
 #pragma unroll
         for (int r = 0; r < 32; ++r) {
-            acc += sA[(32 * seg + r) * LG + col];
+            const int row = 32 * seg + r;
+            acc += (row < n) ? sA[row * LG + col] : 0.f;
             x[r] = acc;
         }
         float pre = __shfl_up_sync(0xffffffffu, acc, 1, 2);
@@ -254,7 +246,7 @@ __global__ void __launch_bounds__(PT, 2)
         float hi = -INFINITY, lo = INFINITY;
 #pragma unroll
         for (int r = 0; r < 32; ++r) {
-            x[r] += pre;
+            x[r] = (x[r] + pre) * LOG2E;
             if (32 * seg + r < n) {
                 hi = fmaxf(hi, x[r]);
                 lo = fminf(lo, x[r]);
@@ -274,23 +266,28 @@ __global__ void __launch_bounds__(PT, 2)
         wide_col = (hi - lo) > PREP_RANGE_LOG2;
     }
     const bool wide = __syncthreads_or(wide_col) != 0;
-    if (tid == 0) f.WIDE[ch] = wide ? 1 : 0;
-    bool ok = true;
-    if (!wide) {
-        // a2 operands (bf16), one pass over the row chunks of this thread: A1 rows 0..63
-        // beta_i k_i alpha_i, rows 64..127 s q_i alpha_i; B1 rows j: k_j / alpha_j; V as loaded.
-        // Q_g = s q alpha 2^c and F = K 2^(G2_last - G2) = k 2^(G2_last - c) / alpha go to HBM.
+    if (tid == 0 && ok) f.WIDE[ch] = wide ? 1 : 0;
+    if (!wide && ok) {
+        // a2 operands (bf16), in place over the loaded tiles, one pass over the row chunks of this
+        // thread: A1 rows 0..63 beta_i k_i alpha_i, rows 64..127 s q_i alpha_i; B1 rows j:
+        // k_j / alpha_j; rows past the chunk end zero. Q_g = s q alpha 2^c and
+        // F = K 2^(G2_last - G2) = k 2^(G2_last - c) / alpha go to HBM.
         float c2r[8], alr[8];
 #pragma unroll
         for (int e = 0; e < 8; e += 4) {
             *reinterpret_cast<float4*>(c2r + e) = *reinterpret_cast<const float4*>(sC2 + c8 + e);
             *reinterpret_cast<float4*>(alr + e) = *reinterpret_cast<const float4*>(sAL + c8 + e);
         }
+        constexpr int NU = BT * D / 8 / PT;   // 16-byte chunks per thread
 #pragma unroll
         for (int u = 0; u < NU; ++u) {
             const int i = (tid + PT * u) >> 4;
-            const bf16* kv = reinterpret_cast<const bf16*>(&kr4[u]);
-            const bf16* qv = reinterpret_cast<const bf16*>(&qr4[u]);
+            unsigned char* kp = base + P_B1 + tc::sw128_off(BT, i, c8 * 2);
+            unsigned char* qp = base + P_A1 + tc::sw128_off(2 * BT, BT + i, c8 * 2);
+            uint4 kr = *reinterpret_cast<const uint4*>(kp), qr = *reinterpret_cast<const uint4*>(qp);
+            if (i >= n) kr = qr = make_uint4(0, 0, 0, 0);
+            const bf16* kv = reinterpret_cast<const bf16*>(&kr);
+            const bf16* qv = reinterpret_cast<const bf16*>(&qr);
             float al[8];
             *reinterpret_cast<float4*>(al) = *reinterpret_cast<const float4*>(sA + i * LG + c8);
             *reinterpret_cast<float4*>(al + 4) = *reinterpret_cast<const float4*>(sA + i * LG + c8 + 4);
@@ -310,9 +307,8 @@ __global__ void __launch_bounds__(PT, 2)
                 pf[e / 2] = tc::pack_bf16(z0 * alr[e], z1 * alr[e + 1]);
             }
             *reinterpret_cast<uint4*>(base + P_A1 + tc::sw128_off(2 * BT, i, c8 * 2)) = make_uint4(pe[0], pe[1], pe[2], pe[3]);
-            *reinterpret_cast<uint4*>(base + P_A1 + tc::sw128_off(2 * BT, BT + i, c8 * 2)) = make_uint4(pq[0], pq[1], pq[2], pq[3]);
-            *reinterpret_cast<uint4*>(base + P_B1 + tc::sw128_off(BT, i, c8 * 2)) = make_uint4(pz[0], pz[1], pz[2], pz[3]);
-            *reinterpret_cast<uint4*>(base + P_V + tc::sw128_off(BT, i, c8 * 2)) = vr4[u];
+            *reinterpret_cast<uint4*>(qp) = make_uint4(pq[0], pq[1], pq[2], pq[3]);
+            *reinterpret_cast<uint4*>(kp) = make_uint4(pz[0], pz[1], pz[2], pz[3]);
             *reinterpret_cast<uint4*>(f.QG + ch * BT * D + tile_el(BT, i, c8)) = make_uint4(pg[0], pg[1], pg[2], pg[3]);
             *reinterpret_cast<uint4*>(f.KG + ch * BT * D + tile_el(BT, i, c8)) = make_uint4(pf[0], pf[1], pf[2], pf[3]);
         }
@@ -743,9 +739,13 @@ cudaError_t run_prep(const Shape& s, const void* q, const void* k, const void* v
                      const float* g, Table t, FwdTC f, cudaStream_t st) {
     cudaError_t e = set_smem_once<k_prep_tc<GATE, BWD>>(PREP_SMEM);
     if (e != cudaSuccess) return e;
+    CUtensorMap mq, mk, mv, mg;
+    memset(&mg, 0, sizeof(mg));
+    if (!tmap_rows_bf16(&mq, q, s.Ttot, s.H, D) || !tmap_rows_bf16(&mk, k, s.Ttot, s.H, D) ||
+        !tmap_rows_bf16(&mv, v, s.Ttot, s.H, D) || (GATE == 2 && !tmap_rows_f32(&mg, g, s.Ttot, s.H, D)))
+        return cudaErrorInvalidValue;
     dim3 grid(s.NC, s.H);
-    k_prep_tc<GATE, BWD><<<grid, PT, PREP_SMEM, st>>>(s, (const bf16*)q, (const bf16*)k, (const bf16*)v,
-                                                      (const bf16*)beta, g, t, f);
+    k_prep_tc<GATE, BWD><<<grid, PT, PREP_SMEM, st>>>(s, mq, mk, mv, mg, (const bf16*)beta, g, t, f);
     return cudaGetLastError();
 }
 
