@@ -28,6 +28,8 @@
 // wider than the single-anchor limit (sub-chunk anchoring for per-channel
 // gates; strong scalar decay, where the log-gate gradient cancels heavily)
 // are left to the fp32 CUDA-core consumers.
+#include <string.h>
+
 #include "kda_internal.cuh"
 #include "tc.cuh"
 
@@ -362,8 +364,9 @@ constexpr int X_EQ = 0;          // [E_a^T | Q_a^T] tf32 [128][128] 64 KB
 constexpr int X_KZ = 65536;      // (K zeta)^T tf32 [128][64]    32 KB
 constexpr int X_DH = 98304;      // [D ; H_q]^T tf32 [64][128]   32 KB
 constexpr int X_BYTES = 131072;
-constexpr int C_A = X_BYTES;                      // G2, then alpha = 2^(G2 - c), fp32 [64][129]
-constexpr int C_K = C_A + 4 * BT * LG;            // k bf16 [64][128], SW128 rows (conflict-free row and column reads)
+constexpr int C_A = X_BYTES;                      // g (dense rows, as TMA lands them), then alpha
+                                                  // = 2^(G2 - c) at aidx(row, col), fp32 [64][128]
+constexpr int C_K = C_A + 4 * BT * D;             // k bf16 [64][128], SW128 rows (conflict-free row and column reads)
 constexpr int C_Q = C_K + 2 * BT * D;             // q bf16 [64][128], SW128 rows
 constexpr int C_MISC = C_Q + 2 * BT * D;          // small arrays (floats)
 constexpr int M_BETA = 0, M_C2 = 64, M_AL = 192, M_LAMB = 320, M_DBW = 448, M_ROWP = 512,
@@ -373,6 +376,11 @@ constexpr int CONS_SMEM = C_BAR + 64 + 1024;
 
 __device__ __forceinline__ float bfx(const bf16* p) { return __bfloat162float(*p); }
 
+// Position of alpha(row, col) in its dense [64][128] tile: the column is XORed
+// with the row (mod 32), so reads along a row or along a column by consecutive
+// lanes fall in distinct banks.
+__device__ __forceinline__ int aidx(int r, int c) { return r * D + (c ^ (r & 31)); }
+
 // Element (r, col) of a [64][128] bf16 tile stored in SW128 rows.
 __device__ __forceinline__ float ldsw(const unsigned char* tile, int r, int col) {
     return __bfloat162float(*reinterpret_cast<const bf16*>(tile + tc::sw128_off(BT, r, col * 2)));
@@ -380,9 +388,10 @@ __device__ __forceinline__ float ldsw(const unsigned char* tile, int r, int col)
 
 template <int GATE>
 __global__ void __launch_bounds__(CT, 1)
-    k_bwd_consumer_tc(Shape s, const bf16* __restrict__ q, const bf16* __restrict__ k,
+    k_bwd_consumer_tc(Shape s, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                      const __grid_constant__ CUtensorMap tmo, const __grid_constant__ CUtensorMap tmg,
                       const bf16* __restrict__ v, const bf16* __restrict__ beta, const float* __restrict__ g,
-                      const bf16* __restrict__ dout, Table t, FwdTC f, BwdTC b, bf16* __restrict__ dq,
+                      Table t, FwdTC f, BwdTC b, bf16* __restrict__ dq,
                       bf16* __restrict__ dk, bf16* __restrict__ dv, bf16* __restrict__ dbeta,
                       float* __restrict__ dg) {
     extern __shared__ unsigned char smem_raw[];
@@ -400,8 +409,9 @@ __global__ void __launch_bounds__(CT, 1)
     float* sRowP = sm + M_ROWP;   // [4][64] partial <k_i, gamma E_bar_i>
     float* sEndP = sm + M_ENDP;   // [4][128] partial sum_j F_j . F_bar_j
     float* sRow = sm + M_ROW;     // [64] scalar-gate row sums
-    uint64_t* bar = reinterpret_cast<uint64_t*>(base + C_BAR);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 1);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(base + C_BAR);   // MMA completions
+    uint64_t* bld = bar + 1;                                       // input tiles
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 2);
     const uint32_t sb = tc::smem_u32(base);
 
     const int c = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -413,75 +423,53 @@ __global__ void __launch_bounds__(CT, 1)
     if (GATE != 0 && f.WIDE[ch]) return;  // wide gate range: fp32 CUDA-core consumers
     const int tok0 = t.chunk_tok0[c];
     const float scale = s.scale;
-    const size_t rowstride = (size_t)H * D;
 
+    // token-major inputs by TMA: k, q (SW128 rows), dO (rows 0..63 of the [dO ; P] tile), g (fp32
+    // rows). Rows past the chunk end hold the following tokens (or zeros past the tensor); every
+    // use below either masks them or only reaches rows that are never stored.
     if (tid == 0) {
         tc::mbar_init(bar, 1);
+        tc::mbar_init(bld, 1);
         tc::fence_mbar_init();
+        tc::mbar_arrive_expect_tx(bld, 6 * 8192 + (GATE == 2 ? BT * D * 4 : 0));
+        tc::tma_load3(sb + C_K, &tmk, 0, h, tok0, bld);
+        tc::tma_load3(sb + C_K + 8192, &tmk, 64, h, tok0, bld);
+        tc::tma_load3(sb + C_Q, &tmq, 0, h, tok0, bld);
+        tc::tma_load3(sb + C_Q + 8192, &tmq, 64, h, tok0, bld);
+        tc::tma_load3(sb + X_OP, &tmo, 0, h, tok0, bld);
+        tc::tma_load3(sb + X_OP + 16384, &tmo, 64, h, tok0, bld);
+        if (GATE == 2) tc::tma_load3(sb + C_A, &tmg, 0, h, tok0, bld);
     }
     if (warp == 0) {
         tc::tmem_alloc(tslot, 512);
         tc::tmem_relinquish();
     }
-    // phase A operands by cp.async: [dO ; P] (one 128-row tile), R, S, S+bar
+    // phase A operands by cp.async: P (rows 64..127 of [dO ; P]), R, S, S+bar
     {
-        const bf16* dO0 = dout + ((size_t)tok0 * H + h) * D;
         const bf16* P0 = b.P + ch * BT * D;
-        for (int idx = tid; idx < 2 * BT * 16; idx += CT) {
+        for (int idx = tid; idx < BT * 16; idx += CT) {
             const int r = idx >> 4, cc = idx & 15;
-            const bool isO = r < BT;
-            const bool in = !isO || r < n;
-            const bf16* src = isO ? dO0 + (in ? (size_t)r * rowstride + cc * 8 : 0) : P0 + (size_t)(r - BT) * D + cc * 8;
-            tc::cp_async16(sb + X_OP + tc::sw128_off(2 * BT, r, cc * 16), src, in ? 16u : 0u);
+            tc::cp_async16(sb + X_OP + tc::sw128_off(2 * BT, BT + r, cc * 16), P0 + (size_t)r * D + cc * 8);
         }
         load_tile<BT, D, CT, BT + D>(sb + X_RS, f.R + ch * BT * D, D, BT, tid, 0);
         load_tile<D, D, CT, BT + D>(sb + X_RS, f.HS + ch * D * D, D, D, tid, BT);
         load_tile<D, D, CT>(sb + X_SB, b.SBP + ch * D * D, D, D, tid);
         tc::cp_async_commit();
     }
-    // raw inputs: k, q (bf16 rows), g (log2 units), beta; v stays in registers for dv
+    // v stays in registers for dv; beta; the G tile for a scalar gate (or zeros)
     constexpr int NU = BT * D / 8 / CT;
     uint4 vr4[NU];
-    {
-        constexpr int NG = BT * D / 4 / CT;
-        uint4 kr4[NU], qr4[NU];
 #pragma unroll
-        for (int u = 0; u < NU; ++u) {
-            const int ci = tid + CT * u, r = ci >> 4, c8 = (ci & 15) * 8;
-            kr4[u] = qr4[u] = vr4[u] = make_uint4(0, 0, 0, 0);
-            if (r < n) {
-                const size_t off = ((size_t)(tok0 + r) * H + h) * D + c8;
-                kr4[u] = __ldg(reinterpret_cast<const uint4*>(k + off));
-                qr4[u] = __ldg(reinterpret_cast<const uint4*>(q + off));
-                vr4[u] = __ldg(reinterpret_cast<const uint4*>(v + off));
-            }
-        }
-        float4 gr4[NG];
-#pragma unroll
-        for (int u = 0; u < NG; ++u) {
-            const int ci = tid + CT * u, r = ci >> 5, c4 = (ci & 31) * 4;
-            gr4[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (r < n) {
-                if (GATE == 2) gr4[u] = __ldg(reinterpret_cast<const float4*>(g + ((size_t)(tok0 + r) * H + h) * D + c4));
-                if (GATE == 1) {
-                    const float x = __ldg(g + (size_t)(tok0 + r) * H + h);
-                    gr4[u] = make_float4(x, x, x, x);
-                }
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < NU; ++u) {
-            const int ci = tid + CT * u, r = ci >> 4, c8 = (ci & 15) * 8;
-            *reinterpret_cast<uint4*>(base + C_K + tc::sw128_off(BT, r, c8 * 2)) = kr4[u];
-            *reinterpret_cast<uint4*>(base + C_Q + tc::sw128_off(BT, r, c8 * 2)) = qr4[u];
-        }
-#pragma unroll
-        for (int u = 0; u < NG; ++u) {
-            const int ci = tid + CT * u, r = ci >> 5, c4 = (ci & 31) * 4;
-            sA[r * LG + c4] = gr4[u].x * LOG2E;
-            sA[r * LG + c4 + 1] = gr4[u].y * LOG2E;
-            sA[r * LG + c4 + 2] = gr4[u].z * LOG2E;
-            sA[r * LG + c4 + 3] = gr4[u].w * LOG2E;
+    for (int u = 0; u < NU; ++u) {
+        const int ci = tid + CT * u, r = ci >> 4, c8 = (ci & 15) * 8;
+        vr4[u] = make_uint4(0, 0, 0, 0);
+        if (r < n) vr4[u] = __ldg(reinterpret_cast<const uint4*>(v + ((size_t)(tok0 + r) * H + h) * D + c8));
+    }
+    if (GATE != 2) {
+        for (int idx = tid; idx < BT * D / 4; idx += CT) {
+            const int r = idx >> 5, c4 = (idx & 31) * 4;
+            const float x = (GATE == 1 && r < n) ? __ldg(g + (size_t)(tok0 + r) * H + h) : 0.f;
+            *reinterpret_cast<float4*>(sA + r * D + c4) = make_float4(x, x, x, x);
         }
     }
     if (tid < BT) sBeta[tid] = (tid < n) ? bfx(beta + (size_t)(tok0 + tid) * H + h) : 0.f;
@@ -491,6 +479,14 @@ __global__ void __launch_bounds__(CT, 1)
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tb = *tslot;
+    bool ok = wait_all(bld, 0, t.err);
+    if (!ok && tid == 0) tc::mbar_wait(bld, 0);   // let late tiles land before the CTA can leave
+    if (!ok) {   // (device error recorded; the host reports it)
+        tc::fence_before_sync();
+        __syncthreads();
+        if (warp == 0) tc::tmem_dealloc(tb, 512);
+        return;
+    }
     // TMEM columns: [0,64) [H_q ; -D] -> [H_q ; D] ; [64,192) [dO S^T ; P S^T] ;
     // [192,256) F_bar^T ; [256,384) [T_q ; T_e] ; [384,448) T_y^T
     if (warp == 0) {
@@ -514,9 +510,11 @@ __global__ void __launch_bounds__(CT, 1)
         float acc = 0.f;
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
-            acc += sA[(16 * seg + r) * LG + col];
-            x[r] = acc;
+            const int row = 16 * seg + r;
+            acc += (row < n) ? sA[row * D + col] : 0.f;
+            x[r] = acc * LOG2E;
         }
+        acc *= LOG2E;
         float pre = __shfl_up_sync(0xffffffffu, acc, 1, 4);
         if (seg < 1) pre = 0.f;
         float t2 = __shfl_up_sync(0xffffffffu, acc + pre, 2, 4);
@@ -537,8 +535,9 @@ __global__ void __launch_bounds__(CT, 1)
         lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, 2));
         const float cc = (GATE == 0) ? 0.f : 0.5f * (hi + lo);
         const float glast = __shfl_sync(0xffffffffu, x[15], (lane & ~3) | 3);
+        __syncthreads();   // every g read before alpha overwrites the tile at swizzled positions
 #pragma unroll
-        for (int r = 0; r < 16; ++r) sA[(16 * seg + r) * LG + col] = exp2f(x[r] - cc);
+        for (int r = 0; r < 16; ++r) sA[aidx(16 * seg + r, col)] = exp2f(x[r] - cc);
         if (seg == 0) {
             sC2[col] = exp2f(cc);
             sAL[col] = exp2f(glast - cc);
@@ -584,7 +583,7 @@ __global__ void __launch_bounds__(CT, 1)
         for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o, 16);
         if (cc == 0) sDbw[r] = acc;
     }
-    bool ok = wait_all(bar, 0, t.err);
+    ok = wait_all(bar, 0, t.err);
     if (ok) {
         tc::fence_after_sync();
         // ---- epilogue A: mask [H_q ; -D] into [H_q ; D] (scalar gate: fold the pairwise decay
@@ -598,12 +597,12 @@ __global__ void __launch_bounds__(CT, 1)
             tc::tmem_wait_ld();
             const bool isH = row < BT;
             const int i = isH ? row : row - BT;
-            const float ai = sA[i * LG];
+            const float ai = sA[aidx(i, 0)];
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
                 const int j = cb0 + jj;
                 float x = (i < n && (isH ? j <= i : j < i)) ? (isH ? a[jj] : -a[jj]) : 0.f;
-                if (GATE == 1) x *= fminf(ai * tc::rcp_approx(sA[j * LG]), 1.f);
+                if (GATE == 1) x *= fminf(ai * tc::rcp_approx(sA[aidx(j, 0)]), 1.f);
                 a[jj] = x;
                 const int kidx = isH ? BT + i : i;   // K order of T_y^T: D rows first, then H_q rows
                 *reinterpret_cast<float*>(base + X_DH + tc::sw128_off(BT, j, kidx * 4)) = x;
@@ -619,8 +618,8 @@ __global__ void __launch_bounds__(CT, 1)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int j = 4 * cc + e;
-                const float kv = ldsw(sK, j, kr);
-                pv[e] = (GATE == 2) ? kv * tc::rcp_approx(sA[j * LG + kr]) : kv;
+                const float kv = (j < n) ? ldsw(sK, j, kr) : 0.f;
+                pv[e] = (GATE == 2) ? kv * tc::rcp_approx(sA[aidx(j, kr)]) : kv;
             }
             *reinterpret_cast<float4*>(base + X_KZ + tc::sw128_off(D, kr, cc * 16)) = val;
         }
@@ -633,8 +632,8 @@ __global__ void __launch_bounds__(CT, 1)
             for (int e = 0; e < 4; ++e) {
                 const int kk = 4 * cc + e;
                 const int j = kk & (BT - 1);
-                const float al = (GATE == 2) ? sA[j * LG + kr] : 1.f;
-                pv[e] = (kk < BT) ? sBeta[j] * ldsw(sK, j, kr) * al : scale * ldsw(sQ, j, kr) * al;
+                const float al = (GATE == 2) ? sA[aidx(j, kr)] : 1.f;
+                pv[e] = (j >= n) ? 0.f : (kk < BT) ? sBeta[j] * ldsw(sK, j, kr) * al : scale * ldsw(sQ, j, kr) * al;
             }
             *reinterpret_cast<float4*>(base + X_EQ + tc::sw128_off(D, kr, cc * 16)) = val;
         }
@@ -686,7 +685,7 @@ __global__ void __launch_bounds__(CT, 1)
 #pragma unroll
                 for (int jj = 0; jj < 16; ++jj) {
                     const int kr = cb0 + cb + jj;
-                    const float al = sA[i * LG + kr];
+                    const float al = sA[aidx(i, kr)];
                     const float fac = (GATE == 2) ? al : 1.f;      // alpha (unit: folded / no gate)
                     const float gam = al * sC2[kr];                 // gamma = 2^G2
                     const float xq = __bfloat162float(xv[cb + jj]);
@@ -731,7 +730,7 @@ __global__ void __launch_bounds__(CT, 1)
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
                 const int j = cb0 + jj;
-                const float rinv = tc::rcp_approx(sA[j * LG + kr]);
+                const float rinv = tc::rcp_approx(sA[aidx(j, kr)]);
                 const float ze = (GATE == 2) ? rinv : 1.f;
                 const float dec = al_last * rinv;                   // lambda / gamma_j
                 const float Yt = ze * ty[jj] + fb[jj] * dec;        // Y_bar / gamma
@@ -815,10 +814,14 @@ cudaError_t run_consumer(const Shape& s, const void* q, const void* k, const voi
                          void* dv, void* dbeta, float* dg, cudaStream_t st) {
     cudaError_t e = set_smem_once<k_bwd_consumer_tc<GATE>>(CONS_SMEM);
     if (e != cudaSuccess) return e;
+    CUtensorMap mq, mk, mo, mg;
+    memset(&mg, 0, sizeof(mg));
+    if (!tmap_rows_bf16(&mq, q, s.Ttot, s.H, D) || !tmap_rows_bf16(&mk, k, s.Ttot, s.H, D) ||
+        !tmap_rows_bf16(&mo, dout, s.Ttot, s.H, D) || (GATE == 2 && !tmap_rows_f32(&mg, g, s.Ttot, s.H, D)))
+        return cudaErrorInvalidValue;
     dim3 grid(s.NC, s.H);
-    k_bwd_consumer_tc<GATE><<<grid, CT, CONS_SMEM, st>>>(
-        s, (const bf16*)q, (const bf16*)k, (const bf16*)v, (const bf16*)beta, g, (const bf16*)dout, t, f, b,
-        (bf16*)dq, (bf16*)dk, (bf16*)dv, (bf16*)dbeta, dg);
+    k_bwd_consumer_tc<GATE><<<grid, CT, CONS_SMEM, st>>>(s, mq, mk, mo, mg, (const bf16*)v, (const bf16*)beta, g, t, f,
+                                                         b, (bf16*)dq, (bf16*)dk, (bf16*)dv, (bf16*)dbeta, dg);
     return cudaGetLastError();
 }
 
