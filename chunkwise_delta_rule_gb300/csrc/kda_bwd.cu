@@ -28,8 +28,9 @@ namespace {
 
 constexpr int SL = 32;  // value columns of S per slice in k_bwd_dstate
 
-// IT: element type of the P, R, S and S+bar inputs (fp32 here, bf16 when
-// finishing the wide chunks of the tensor-core path, selected by `only`).
+// IT: element type of the P, R, S and S+bar inputs: fp32 row-major here, bf16
+// tile images (tile_el) when finishing the wide chunks of the tensor-core
+// path, selected by `only`.
 template <typename TI, typename IT, int D>
 __global__ void __launch_bounds__(NTHREADS, 1)
     k_bwd_dstate(Shape s, const TI* __restrict__ dout, const TI* __restrict__ v,
@@ -53,13 +54,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (only && !only[ch]) return;
     const int lane = tid & 31, warp = tid >> 5;
 
+    constexpr bool IMG = sizeof(IT) == 2;
     const IT* P = Pin + ch * BT * D;
     const IT* R = Rin + ch * BT * D;
     for (int idx = tid; idx < BT * D; idx += NTHREADS) {
         const int r = idx / D, col = idx % D;
+        const int e = IMG ? tile_el(BT, r, col) : idx;
         sO[r * LD + col] = (r < len) ? ld(dout + ((size_t)(tok0 + r) * H + h) * D + col) : 0.f;
-        sP[r * LD + col] = ld(P + idx);
-        sR[r * LD + col] = ld(R + idx);
+        sP[r * LD + col] = ld(P + e);
+        sR[r * LD + col] = ld(R + e);
     }
     __syncthreads();
     // dv = beta P and <v_i, P_i>, one warp per row
@@ -115,8 +118,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         __syncthreads();
         for (int idx = tid; idx < D * SL; idx += NTHREADS) {
             const int r = idx / SL, cc = idx % SL;
-            sS[r * LS + cc] = ld(SIN + (size_t)r * D + vs + cc);
-            sT[r * LS + cc] = ld(SBP + (size_t)r * D + vs + cc);
+            const size_t e = IMG ? (size_t)tile_el(D, r, vs + cc) : (size_t)r * D + vs + cc;
+            sS[r * LS + cc] = ld(SIN + e);
+            sT[r * LS + cc] = ld(SBP + e);
         }
         __syncthreads();
         tile_gemm<BT, D, 8, TN>(aQ, 0, SL, [&](int m, int kk) { return sO[m * LD + vs + kk]; },

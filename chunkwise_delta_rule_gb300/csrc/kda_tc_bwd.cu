@@ -46,21 +46,6 @@ __device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, int32_t
     return ok;
 }
 
-// Copies a row-major bf16 [R][C] global tile (row stride `ld` elements) into
-// rows row0.. of a K-major SW128 smem tile of RT rows; rows >= valid are
-// zero-filled.
-template <int R, int C, int NT, int RT = R>
-__device__ __forceinline__ void load_tile(uint32_t sbase, const bf16* src, size_t ld, int valid, int tid,
-                                          int row0 = 0) {
-    constexpr int CPR = C * 2 / 16;
-    for (int idx = tid; idx < R * CPR; idx += NT) {
-        const int r = idx / CPR, cc = idx % CPR;
-        const bool in = r < valid;
-        tc::cp_async16(sbase + tc::sw128_off(RT, row0 + r, cc * 16), src + (in ? (size_t)r * ld + cc * 8 : 0),
-                       in ? 16u : 0u);
-    }
-}
-
 // ====================================================== k_bwd_scan_tc
 constexpr int ST = 256;            // compute warps: warps w and w+4 share lane quarter w%4, split columns
 constexpr int ST_ALL = ST + 32;    // + one warp that issues the MMAs and the bulk fills
@@ -189,7 +174,7 @@ __device__ __forceinline__ void bscan_compute(const Shape& s, const bf16* __rest
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
             const int cb = kb + 16 * q4;
-            tc::warp_store_t16(tst, sv[q4], SBP + (size_t)cb * D + 32 * quad, D, 16, lane);
+            tc::warp_store_t16_img(tst, sv[q4], SBP, D, cb, 32 * quad, lane);
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) sv[q4][jj] *= sLam[cb + jj];
             tc::tmem_st16(tl + cb, sv[q4]);
@@ -203,8 +188,8 @@ __device__ __forceinline__ void bscan_compute(const Shape& s, const bf16* __rest
             tc::tmem_ld16(tp + ib, pv[0]);
             tc::tmem_ld16(tp + ib + 16, pv[1]);
             tc::tmem_wait_ld();
-            tc::warp_store_t16(tst, pv[0], P + (size_t)ib * D + 32 * quad, D, 16, lane);
-            tc::warp_store_t16(tst, pv[1], P + (size_t)(ib + 16) * D + 32 * quad, D, 16, lane);
+            tc::warp_store_t16_img(tst, pv[0], P, BT, ib, 32 * quad, lane);
+            tc::warp_store_t16_img(tst, pv[1], P, BT, ib + 16, 32 * quad, lane);
         }
         if (c - 1 >= c0) bscan_load_do(dout, lenm, tok0m, H, h, ib, vcol, dnext);
         // 3. R_bar^T -> bf16 A operands R_bar^T and -R_bar^T, handed over
@@ -240,8 +225,8 @@ __device__ __forceinline__ void bscan_compute(const Shape& s, const bf16* __rest
         tc::tmem_ld16(tp + ib, pv[0]);
         tc::tmem_ld16(tp + ib + 16, pv[1]);
         tc::tmem_wait_ld();
-        tc::warp_store_t16(tst, pv[0], P + (size_t)ib * D + 32 * quad, D, 16, lane);
-        tc::warp_store_t16(tst, pv[1], P + (size_t)(ib + 16) * D + 32 * quad, D, 16, lane);
+        tc::warp_store_t16_img(tst, pv[0], P, BT, ib, 32 * quad, lane);
+        tc::warp_store_t16_img(tst, pv[1], P, BT, ib + 16, 32 * quad, lane);
     }
     if (ok && dh0) {
 #pragma unroll 1
@@ -431,7 +416,19 @@ __global__ void __launch_bounds__(CT, 1)
         tc::mbar_init(bar, 1);
         tc::mbar_init(bld, 1);
         tc::fence_mbar_init();
-        tc::mbar_arrive_expect_tx(bld, 6 * 8192 + (GATE == 2 ? BT * D * 4 : 0));
+        // P, R, S and S+bar are tile images: one bulk copy per atom column of the
+        // [dO ; P] and [R ; S] tiles, one for S+bar
+        tc::mbar_arrive_expect_tx(bld, 6 * 8192 + (GATE == 2 ? BT * D * 4 : 0) + 2 * 16384 + 2 * 32768);
+        const unsigned char* P0 = reinterpret_cast<const unsigned char*>(b.P + ch * BT * D);
+        const unsigned char* R0 = reinterpret_cast<const unsigned char*>(f.R + ch * BT * D);
+        const unsigned char* S0 = reinterpret_cast<const unsigned char*>(f.HS + ch * D * D);
+        tc::bulk_g2s(sb + X_OP + 8192, P0, 8192, bld);
+        tc::bulk_g2s(sb + X_OP + 16384 + 8192, P0 + 8192, 8192, bld);
+        tc::bulk_g2s(sb + X_RS, R0, 8192, bld);
+        tc::bulk_g2s(sb + X_RS + 24576, R0 + 8192, 8192, bld);
+        tc::bulk_g2s(sb + X_RS + 8192, S0, 16384, bld);
+        tc::bulk_g2s(sb + X_RS + 24576 + 8192, S0 + 16384, 16384, bld);
+        tc::bulk_g2s(sb + X_SB, b.SBP + ch * D * D, 32768, bld);
         tc::tma_load3(sb + C_K, &tmk, 0, h, tok0, bld);
         tc::tma_load3(sb + C_K + 8192, &tmk, 64, h, tok0, bld);
         tc::tma_load3(sb + C_Q, &tmq, 0, h, tok0, bld);
@@ -443,18 +440,6 @@ __global__ void __launch_bounds__(CT, 1)
     if (warp == 0) {
         tc::tmem_alloc(tslot, 512);
         tc::tmem_relinquish();
-    }
-    // phase A operands by cp.async: P (rows 64..127 of [dO ; P]), R, S, S+bar
-    {
-        const bf16* P0 = b.P + ch * BT * D;
-        for (int idx = tid; idx < BT * 16; idx += CT) {
-            const int r = idx >> 4, cc = idx & 15;
-            tc::cp_async16(sb + X_OP + tc::sw128_off(2 * BT, BT + r, cc * 16), P0 + (size_t)r * D + cc * 8);
-        }
-        load_tile<BT, D, CT, BT + D>(sb + X_RS, f.R + ch * BT * D, D, BT, tid, 0);
-        load_tile<D, D, CT, BT + D>(sb + X_RS, f.HS + ch * D * D, D, D, tid, BT);
-        load_tile<D, D, CT>(sb + X_SB, b.SBP + ch * D * D, D, D, tid);
-        tc::cp_async_commit();
     }
     // v stays in registers for dv; beta; the G tile for a scalar gate (or zeros)
     constexpr int NU = BT * D / 8 / CT;
@@ -473,8 +458,6 @@ __global__ void __launch_bounds__(CT, 1)
         }
     }
     if (tid < BT) sBeta[tid] = (tid < n) ? bfx(beta + (size_t)(tok0 + tid) * H + h) : 0.f;
-    tc::cp_async_wait_all();
-    tc::fence_async_smem();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();

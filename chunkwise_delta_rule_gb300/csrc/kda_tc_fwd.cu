@@ -576,7 +576,7 @@ __device__ __forceinline__ void fscan_compute(const Shape& s, const float* __res
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
             const int cb = kb + 16 * q4;
-            if (MODE & 2) tc::warp_store_t16(tst, sv[q4], f.HS + ch * D * D + (size_t)cb * D + 32 * quad, D, 16, lane);
+            if (MODE & 2) tc::warp_store_t16_img(tst, sv[q4], f.HS + ch * D * D, D, cb, 32 * quad, lane);
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) sv[q4][jj] *= sLam[cb + jj];
             tc::tmem_st16(tl + cb, sv[q4]);
@@ -611,7 +611,7 @@ __device__ __forceinline__ void fscan_compute(const Shape& s, const float* __res
         if (MODE & 2) {
 #pragma unroll
             for (int cq = 0; cq < 32; cq += 16)
-                tc::warp_store_t16(tst, rv[cq / 16], f.R + ch * BT * D + (size_t)(ib + cq) * D + 32 * quad, D, 16, lane);
+                tc::warp_store_t16_img(tst, rv[cq / 16], f.R + ch * BT * D, BT, ib + cq, 32 * quad, lane);
         }
     }
     if (c1 > c0) {

@@ -15,6 +15,9 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include "kda_internal.cuh"
+
+
 namespace kda {
 namespace tc {
 
@@ -309,6 +312,21 @@ __device__ __forceinline__ void warp_store_t16(__nv_bfloat16* stg, const float (
         const int r = p >> 2, q = p & 3;
         if (r < ncols)
             *reinterpret_cast<uint4*>(dst + (size_t)r * ld + q * 8) = *reinterpret_cast<const uint4*>(stg + r * 40 + q * 8);
+    }
+    __syncwarp();
+}
+// The same block written into a tile image with R rows (see tile_el): rows
+// row0.. and 32 columns from col0 (a multiple of 8).
+__device__ __forceinline__ void warp_store_t16_img(__nv_bfloat16* stg, const float (&a)[16], __nv_bfloat16* tile,
+                                                   int R, int row0, int col0, int lane) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) stg[j * 40 + lane] = __float2bfloat16_rn(a[j]);
+    __syncwarp();
+#pragma unroll
+    for (int p = lane; p < 64; p += 32) {
+        const int r = p >> 2, q = p & 3;
+        *reinterpret_cast<uint4*>(tile + ::kda::tile_el(R, row0 + r, col0 + 8 * q)) =
+            *reinterpret_cast<const uint4*>(stg + r * 40 + q * 8);
     }
     __syncwarp();
 }
