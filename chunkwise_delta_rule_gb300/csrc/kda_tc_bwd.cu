@@ -59,21 +59,26 @@ constexpr int S_AQ = 16384;     // C_q [64][64]   8 KB
 constexpr int S_AI = 24576;     // A   [64][64]   8 KB
 constexpr int S_QG = 32768;     // Q_g [64][128] 16 KB
 constexpr int S_W = 49152;      // W   [64][128] 16 KB
-constexpr int B_STG = 65536;
+constexpr int S_DO = 65536;     // dO  [64][128] 16 KB, TMA (read MN-major as the A operand dO^T)
+constexpr int B_STG = 81920;
 constexpr int B_LAM = B_STAGE + 2 * B_STG;     // lambda [128] fp32
 constexpr int B_TST = B_LAM + 512;             // per-warp transpose staging, 8 x 1280 B
 constexpr int B_BAR = B_TST + 8 * 1280;
 constexpr int BSCAN_SMEM = B_BAR + 64 + 1024;
 // TMEM columns: S_bar^T fp32 [0,128), R_bar^T fp32 [128,192), P^T double buffer [192,320);
 // bf16 A operands (two values per column): S+bar^T [320,384), R_bar^T [384,416),
-// -R_bar^T [416,448), dO^T [448,480)
-constexpr int T_RB = 128, T_P = 192, T_AS = 320, T_AR = 384, T_NR = 416, T_DO = 448;
+// -R_bar^T [416,448)
+constexpr int T_RB = 128, T_P = 192, T_AS = 320, T_AR = 384, T_NR = 416;
 
-// Stages the operand tiles of one chunk (stored as tile images) with bulk
-// copies; one thread; completion arrives on `full` as transaction bytes.
-__device__ __forceinline__ void bscan_fill(uint32_t stg, const FwdTC& f, size_t ch, uint64_t* full) {
+// Stages the operand tiles of one chunk (tile images by bulk copies, dO by
+// TMA from the token tensor); one thread; completion arrives on `full` as
+// transaction bytes. dO rows past the chunk end meet zero rows of C_q and Q_g.
+__device__ __forceinline__ void bscan_fill(uint32_t stg, const FwdTC& f, size_t ch, const CUtensorMap* tmo, int h,
+                                           int tok0, uint64_t* full) {
     constexpr uint32_t TILE = BT * D * 2, TQ = BT * BT * 2;
-    tc::mbar_arrive_expect_tx(full, 3 * TILE + 2 * TQ);
+    tc::mbar_arrive_expect_tx(full, 4 * TILE + 2 * TQ);
+    tc::tma_load3(stg + S_DO, tmo, 0, h, tok0, full);
+    tc::tma_load3(stg + S_DO + 8192, tmo, 64, h, tok0, full);
     tc::bulk_g2s(stg + S_KG, f.KG + ch * BT * D, TILE, full);
     tc::bulk_g2s(stg + S_AQ, f.AQK + ch * BT * BT, TQ, full);
     tc::bulk_g2s(stg + S_AI, f.AI + ch * BT * BT, TQ, full);
@@ -81,26 +86,13 @@ __device__ __forceinline__ void bscan_fill(uint32_t stg, const FwdTC& f, size_t 
     tc::bulk_g2s(stg + S_W, f.W + ch * BT * D, TILE, full);
 }
 
-// This thread's half of the dO column of a chunk as packed bf16 pairs (the
-// order of a TMEM A operand row), rows past the chunk end zero.
-__device__ __forceinline__ void bscan_load_do(const bf16* __restrict__ dout, int len, int tok0, int H, int h,
-                                              int ib, int vcol, uint32_t (&pw)[16]) {
-    const uint16_t* src = reinterpret_cast<const uint16_t*>(dout) + ((size_t)(tok0 + ib) * H + h) * D + vcol;
-#pragma unroll
-    for (int i = 0; i < 32; i += 2) {
-        const uint32_t x0 = (ib + i < len) ? src[(size_t)i * H * D] : 0u;
-        const uint32_t x1 = (ib + i + 1 < len) ? src[(size_t)(i + 1) * H * D] : 0u;
-        pw[i / 2] = x0 | (x1 << 16);
-    }
-}
-
-// Compute warps: per chunk (last to first) S+bar^T and dO^T -> bf16 A operands,
-// then (while R_bar runs) S+bar to HBM, S_bar^T <- S+bar^T diag(lambda), P of
-// the previous chunk to HBM, dO of the next chunk; then R_bar^T -> bf16.
-__device__ __forceinline__ void bscan_compute(const Shape& s, const bf16* __restrict__ dout,
-                                              const float* __restrict__ dht, const Table& t, const FwdTC& f,
-                                              const BwdTC& b, float* __restrict__ dh0, unsigned char* base,
-                                              uint64_t* bar, uint32_t tb, int nseq, int h, int c0, int c1) {
+// Compute warps: per chunk (last to first) S+bar^T -> bf16 A operand, then
+// (while R_bar runs) S_bar^T <- S+bar^T diag(lambda); R_bar^T -> bf16 A operands;
+// then, while the state adjoint update runs, S+bar and the previous P to HBM.
+__device__ __forceinline__ void bscan_compute(const Shape& s, const float* __restrict__ dht, const Table& t,
+                                              const FwdTC& f, const BwdTC& b, float* __restrict__ dh0,
+                                              unsigned char* base, uint64_t* bar, uint32_t tb, int nseq, int h,
+                                              int c0, int c1) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = warp & 3, half = warp >> 2;
     float* sLam = reinterpret_cast<float*>(base + B_LAM);
@@ -128,70 +120,54 @@ __device__ __forceinline__ void bscan_compute(const Shape& s, const bf16* __rest
         }
         tc::fence_after_sync();
     };
-    uint32_t dnext[16];
+    // P of a chunk (rows ib..ib+31 of this thread's value column) from its TMEM buffer to HBM
+    auto store_p = [&](int cc, int buf) {
+        bf16* P = b.P + ((size_t)cc * H + h) * BT * D;
+        float pv[2][16];
+        const uint32_t tp = tl + T_P + 64 * buf;
+        tc::tmem_ld16(tp + ib, pv[0]);
+        tc::tmem_ld16(tp + ib + 16, pv[1]);
+        tc::tmem_wait_ld();
+        tc::warp_store_t16_img(tst, pv[0], P, BT, ib, 32 * quad, lane);
+        tc::warp_store_t16_img(tst, pv[1], P, BT, ib + 16, 32 * quad, lane);
+    };
     float gln = 0.f;
-    int lenn = 0, tok0n = 0, cp = -1;   // cp: the previous (later) chunk, whose P is pending
-    if (c0 < c1) {
-        lenn = t.chunk_len[c1 - 1];
-        tok0n = t.chunk_tok0[c1 - 1];
-        if (tid < D) gln = f.GL[((size_t)(c1 - 1) * H + h) * D + tid];
-        bscan_load_do(dout, lenn, tok0n, H, h, ib, vcol, dnext);
-    }
+    if (c0 < c1 && tid < D) gln = f.GL[((size_t)(c1 - 1) * H + h) * D + tid];
     for (int c = c1 - 1; c >= c0; --c) {
         const int it = c1 - 1 - c;
         const size_t ch = (size_t)c * H + h;
         if (tid < D) sLam[tid] = exp2f(gln);
-        int lenm = 0, tok0m = 0;
-        if (c - 1 >= c0) {
-            lenm = t.chunk_len[c - 1];
-            tok0m = t.chunk_tok0[c - 1];
-            if (tid < D) gln = f.GL[(ch - H) * D + tid];
-        }
+        if (c - 1 >= c0 && tid < D) gln = f.GL[(ch - H) * D + tid];
         if (it > 0) wait_one(&bar[1], (it - 1) & 1);   // state adjoint update of the later chunk
         tc::named_sync(NB_C, ST);
-        // 1. S+bar^T and dO^T -> bf16 A operands in TMEM, handed to the issuer
+        // 1. S+bar^T -> bf16 A operand in TMEM, handed to the issuer
         float sv[4][16];
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) tc::tmem_ld16(tl + kb + 16 * q4, sv[q4]);
         tc::tmem_wait_ld();
+        uint32_t sp[2][16];   // bf16 S+bar^T, also what goes to HBM
 #pragma unroll
         for (int hq = 0; hq < 2; ++hq) {
-            uint32_t pw[16];
 #pragma unroll
             for (int jj = 0; jj < 8; ++jj) {
-                pw[jj] = tc::pack_bf16(sv[2 * hq][2 * jj], sv[2 * hq][2 * jj + 1]);
-                pw[8 + jj] = tc::pack_bf16(sv[2 * hq + 1][2 * jj], sv[2 * hq + 1][2 * jj + 1]);
+                sp[hq][jj] = tc::pack_bf16(sv[2 * hq][2 * jj], sv[2 * hq][2 * jj + 1]);
+                sp[hq][8 + jj] = tc::pack_bf16(sv[2 * hq + 1][2 * jj], sv[2 * hq + 1][2 * jj + 1]);
             }
-            tc::tmem_st16u(tl + T_AS + kb / 2 + 16 * hq, pw);
+            tc::tmem_st16u(tl + T_AS + kb / 2 + 16 * hq, sp[hq]);
         }
-        tc::tmem_st16u(tl + T_DO + ib / 2, dnext);
         tc::tmem_wait_st();
         tc::fence_before_sync();
         tc::named_sync(NB_AS, ST_ALL);
-        // 2. while R_bar runs: S+bar to HBM, S_bar^T <- S+bar^T diag(lambda), P of the later
-        //    chunk, dO of the next chunk
-        bf16* SBP = b.SBP + ch * D * D;
+        // 2. while R_bar runs: S_bar^T <- S+bar^T diag(lambda) (before the update MMAs accumulate)
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
             const int cb = kb + 16 * q4;
-            tc::warp_store_t16_img(tst, sv[q4], SBP, D, cb, 32 * quad, lane);
+            float a[16];
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) sv[q4][jj] *= sLam[cb + jj];
-            tc::tmem_st16(tl + cb, sv[q4]);
+            for (int jj = 0; jj < 16; ++jj) a[jj] = sv[q4][jj] * sLam[cb + jj];
+            tc::tmem_st16(tl + cb, a);
         }
         tc::tmem_wait_st();
-        if (cp >= 0) {
-            wait_one(&bar[2], (it - 1) & 1);
-            bf16* P = b.P + ((size_t)cp * H + h) * BT * D;
-            float pv[2][16];
-            const uint32_t tp = tl + T_P + 64 * ((it - 1) & 1);
-            tc::tmem_ld16(tp + ib, pv[0]);
-            tc::tmem_ld16(tp + ib + 16, pv[1]);
-            tc::tmem_wait_ld();
-            tc::warp_store_t16_img(tst, pv[0], P, BT, ib, 32 * quad, lane);
-            tc::warp_store_t16_img(tst, pv[1], P, BT, ib + 16, 32 * quad, lane);
-        }
-        if (c - 1 >= c0) bscan_load_do(dout, lenm, tok0m, H, h, ib, vcol, dnext);
         // 3. R_bar^T -> bf16 A operands R_bar^T and -R_bar^T, handed over
         wait_one(&bar[0], it & 1);
         {
@@ -213,20 +189,23 @@ __device__ __forceinline__ void bscan_compute(const Shape& s, const bf16* __rest
         tc::tmem_wait_st();
         tc::fence_before_sync();
         tc::named_sync(NB_AR, ST_ALL);
-        cp = c;
+        // 4. while the update runs: S+bar of this chunk and P of the later one to HBM
+        bf16* SBP = b.SBP + ch * D * D;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+            tc::warp_store_t16_img_packed(tst, &sp[q4 >> 1][8 * (q4 & 1)], SBP, D, kb + 16 * q4, 32 * quad, lane);
+        if (it > 0) {
+            // P of the later chunk: one barrier per TMEM buffer, so the commit of this chunk's P
+            // (already possible here) cannot be mistaken for it
+            wait_one(&bar[2 + ((it - 1) & 1)], ((it - 1) >> 1) & 1);
+            store_p(c + 1, (it - 1) & 1);
+        }
     }
     if (c1 > c0) {
         const int last = c1 - 1 - c0;
         wait_one(&bar[1], last & 1);
-        wait_one(&bar[2], last & 1);
-        bf16* P = b.P + ((size_t)c0 * H + h) * BT * D;
-        float pv[2][16];
-        const uint32_t tp = tl + T_P + 64 * (last & 1);
-        tc::tmem_ld16(tp + ib, pv[0]);
-        tc::tmem_ld16(tp + ib + 16, pv[1]);
-        tc::tmem_wait_ld();
-        tc::warp_store_t16_img(tst, pv[0], P, BT, ib, 32 * quad, lane);
-        tc::warp_store_t16_img(tst, pv[1], P, BT, ib + 16, 32 * quad, lane);
+        wait_one(&bar[2 + (last & 1)], (last >> 1) & 1);
+        store_p(c0, last & 1);
     }
     if (ok && dh0) {
 #pragma unroll 1
@@ -240,39 +219,44 @@ __device__ __forceinline__ void bscan_compute(const Shape& s, const bf16* __rest
     }
 }
 
-// Issuer warp: bulk fills (lane 0) and the three MMA groups of every chunk
-// (warp-uniform descriptors, one elected lane issuing).
-__device__ __forceinline__ void bscan_issue(const Shape& s, const Table& t, const FwdTC& f, uint32_t sb,
-                                            uint64_t* bar, uint64_t* full, uint32_t tb, int h, int c0, int c1,
-                                            int& filled, int& waited) {
+// Issuer warp: bulk / TMA fills (lane 0) and the three MMA groups of every
+// chunk (warp-uniform descriptors, one elected lane issuing).
+__device__ __forceinline__ void bscan_issue(const Shape& s, const Table& t, const FwdTC& f,
+                                            const CUtensorMap* tmo, uint32_t sb, uint64_t* bar, uint64_t* full,
+                                            uint32_t tb, int h, int c0, int c1, int& filled, int& waited) {
     const int lane = threadIdx.x & 31;
     const int H = s.H;
     const uint32_t i64 = tc::idesc_bf16(128, 64), m64 = tc::idesc_bf16_bmn(128, 64),
-                   m128 = tc::idesc_bf16_bmn(128, 128);
+                   m128 = tc::idesc_bf16_bmn(128, 128), am64 = tc::idesc_bf16_abmn(128, 64),
+                   am128 = tc::idesc_bf16_abmn(128, 128);
+    int tok_next = (c1 - 2 >= c0) ? t.chunk_tok0[c1 - 2] : 0;   // first token of the chunk filled next
     for (int c = c1 - 1; c >= c0; --c) {
         const int it = c1 - 1 - c, stage = it & 1;
         const uint32_t stg = sb + B_STAGE + stage * B_STG;
+        const uint64_t dO = tc::sdesc_mn(stg + S_DO, BT * 128, 0);
         tc::named_sync(NB_AS, ST_ALL);
         tc::fence_after_sync();
         if (!tc::mbar_wait(&full[stage], (it >> 1) & 1) && lane == 0) atomicOr(t.err, 2);
         {
-            // R_bar^T = S+bar^T F^T + dO^T C_q
+            // R_bar^T = S+bar^T F^T + dO^T C_q (dO^T read MN-major from the staged dO rows)
             const uint64_t dF = tc::sdesc(stg + S_KG), dC = tc::sdesc_mn(stg + S_AQ, BT * 128, 0);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)
                 tc::mma_bf16_ts_w(tb + T_RB, tb + T_AS + 8 * ks, tc::kstep_k(dF, BT, ks), i64, ks > 0);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-                tc::mma_bf16_ts_w(tb + T_RB, tb + T_DO + 8 * ks, tc::kstep_mn(dC, ks), m64, 1);
+                tc::mma_bf16_w(tb + T_RB, tc::kstep_mn(dO, ks), tc::kstep_mn(dC, ks), am64, 1);
             tc::mma_commit_w(&bar[0]);
         }
         if (lane == 0) {
             ++waited;
             if (c - 1 >= c0) {
                 // the other stage is free once every MMA of the later chunk has completed
-                if (it > 0 && !tc::mbar_wait(&bar[2], (it - 1) & 1)) atomicOr(t.err, 2);
-                bscan_fill(sb + B_STAGE + (stage ^ 1) * B_STG, f, (size_t)(c - 1) * H + h, &full[stage ^ 1]);
+                if (it > 0 && !tc::mbar_wait(&bar[2 + ((it - 1) & 1)], ((it - 1) >> 1) & 1)) atomicOr(t.err, 2);
+                bscan_fill(sb + B_STAGE + (stage ^ 1) * B_STG, f, (size_t)(c - 1) * H + h, tmo, h, tok_next,
+                           &full[stage ^ 1]);
                 ++filled;
+                tok_next = (c - 2 >= c0) ? t.chunk_tok0[c - 2] : 0;
             }
         }
         __syncwarp();
@@ -283,27 +267,27 @@ __device__ __forceinline__ void bscan_issue(const Shape& s, const Table& t, cons
             const uint64_t dQ = tc::sdesc_mn(stg + S_QG, BT * 128, 0), dW = tc::sdesc_mn(stg + S_W, BT * 128, 0);
             const uint64_t dA = tc::sdesc_mn(stg + S_AI, BT * 128, 0);
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) tc::mma_bf16_ts_w(tb, tb + T_DO + 8 * ks, tc::kstep_mn(dQ, ks), m128, 1);
+            for (int ks = 0; ks < 4; ++ks) tc::mma_bf16_w(tb, tc::kstep_mn(dO, ks), tc::kstep_mn(dQ, ks), am128, 1);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) tc::mma_bf16_ts_w(tb, tb + T_NR + 8 * ks, tc::kstep_mn(dW, ks), m128, 1);
             tc::mma_commit_w(&bar[1]);
             const uint32_t tP = tb + T_P + 64 * stage;
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) tc::mma_bf16_ts_w(tP, tb + T_AR + 8 * ks, tc::kstep_mn(dA, ks), m64, ks > 0);
-            tc::mma_commit_w(&bar[2]);
+            tc::mma_commit_w(&bar[2 + stage]);
         }
     }
 }
 
 __global__ void __launch_bounds__(ST_ALL, 1)
-    k_bwd_scan_tc(Shape s, const bf16* __restrict__ dout, const float* __restrict__ dht, Table t, FwdTC f,
-                  BwdTC b, float* __restrict__ dh0) {
+    k_bwd_scan_tc(Shape s, const __grid_constant__ CUtensorMap tmo, const float* __restrict__ dht, Table t,
+                  FwdTC f, BwdTC b, float* __restrict__ dh0) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                            ~static_cast<uintptr_t>(1023));
-    uint64_t* bar = reinterpret_cast<uint64_t*>(base + B_BAR);   // R_bar, state adjoint update, P
-    uint64_t* full = bar + 3;                                      // operand stages 0, 1
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 5);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(base + B_BAR);   // R_bar, state adjoint update, P (x2)
+    uint64_t* full = bar + 4;                                      // operand stages 0, 1
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 6);
     const uint32_t sb = tc::smem_u32(base);
     const int nseq = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5;
     const int c0 = t.seq_chunk0[nseq], c1 = t.seq_chunk0[nseq + 1];
@@ -311,10 +295,10 @@ __global__ void __launch_bounds__(ST_ALL, 1)
     int filled = 0, waited = 0;   // bulk fills issued / consumed (issuer lane 0)
 
     if (issuer && (tid & 31) == 0) {
-        for (int i = 0; i < 5; ++i) tc::mbar_init(&bar[i], 1);
+        for (int i = 0; i < 6; ++i) tc::mbar_init(&bar[i], 1);
         tc::fence_mbar_init();
         if (c0 < c1) {
-            bscan_fill(sb + B_STAGE, f, (size_t)(c1 - 1) * s.H + h, &full[0]);
+            bscan_fill(sb + B_STAGE, f, (size_t)(c1 - 1) * s.H + h, &tmo, h, t.chunk_tok0[c1 - 1], &full[0]);
             filled = 1;
         }
     }
@@ -327,9 +311,9 @@ __global__ void __launch_bounds__(ST_ALL, 1)
     tc::fence_after_sync();
     const uint32_t tb = *tslot;
     if (issuer)
-        bscan_issue(s, t, f, sb, bar, full, tb, h, c0, c1, filled, waited);
+        bscan_issue(s, t, f, &tmo, sb, bar, full, tb, h, c0, c1, filled, waited);
     else
-        bscan_compute(s, dout, dht, t, f, b, dh0, base, bar, tb, nseq, h, c0, c1);
+        bscan_compute(s, dht, t, f, b, dh0, base, bar, tb, nseq, h, c0, c1);
     // a bulk fill still in flight (only after a timeout) lands before the CTA leaves
     if (issuer && (tid & 31) == 0)
         for (; waited < filled; ++waited) tc::mbar_wait(&full[waited & 1], (waited >> 1) & 1);
@@ -814,8 +798,10 @@ cudaError_t launch_bwd_scan_tc(const Shape& s, const void* dout, const float* dh
                                float* dh0, cudaStream_t st) {
     cudaError_t e = set_smem_once<k_bwd_scan_tc>(BSCAN_SMEM);
     if (e != cudaSuccess) return e;
+    CUtensorMap mo;
+    if (!tmap_rows_bf16(&mo, dout, s.Ttot, s.H, D)) return cudaErrorInvalidValue;
     dim3 grid(s.N, s.H);
-    k_bwd_scan_tc<<<grid, ST_ALL, BSCAN_SMEM, st>>>(s, (const bf16*)dout, dht, t, f, b, dh0);
+    k_bwd_scan_tc<<<grid, ST_ALL, BSCAN_SMEM, st>>>(s, mo, dht, t, f, b, dh0);
     return cudaGetLastError();
 }
 

@@ -76,6 +76,8 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
 __host__ __device__ constexpr uint32_t idesc_bf16_bmn(int M, int N) { return idesc_bf16(M, N) | (1u << 16); }
 // bf16, MN-major A, K-major B.
 __host__ __device__ constexpr uint32_t idesc_bf16_amn(int M, int N) { return idesc_bf16(M, N) | (1u << 15); }
+// bf16, MN-major A and B.
+__host__ __device__ constexpr uint32_t idesc_bf16_abmn(int M, int N) { return idesc_bf16(M, N) | (3u << 15); }
 __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
     return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
@@ -312,6 +314,22 @@ __device__ __forceinline__ void warp_store_t16(__nv_bfloat16* stg, const float (
         const int r = p >> 2, q = p & 3;
         if (r < ncols)
             *reinterpret_cast<uint4*>(dst + (size_t)r * ld + q * 8) = *reinterpret_cast<const uint4*>(stg + r * 40 + q * 8);
+    }
+    __syncwarp();
+}
+// The same block from packed bf16 pairs (a[2k], a[2k+1] in pw[k]), written into
+// a tile image with R rows: rows row0.. and 32 columns from col0.
+__device__ __forceinline__ void warp_store_t16_img_packed(__nv_bfloat16* stg, const uint32_t* pw, __nv_bfloat16* tile,
+                                                          int R, int row0, int col0, int lane) {
+    uint16_t* s16 = reinterpret_cast<uint16_t*>(stg);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) s16[j * 40 + lane] = (uint16_t)((j & 1) ? (pw[j >> 1] >> 16) : (pw[j >> 1] & 0xffffu));
+    __syncwarp();
+#pragma unroll
+    for (int p = lane; p < 64; p += 32) {
+        const int r = p >> 2, q = p & 3;
+        *reinterpret_cast<uint4*>(tile + ::kda::tile_el(R, row0 + r, col0 + 8 * q)) =
+            *reinterpret_cast<const uint4*>(stg + r * 40 + q * 8);
     }
     __syncwarp();
 }
