@@ -11,6 +11,7 @@ from .ops import (  # noqa: F401
     chunk_kda,
     kda_chunk_bwd,
     kda_chunk_fwd,
+    kda_device_status,
     kda_last_error,
     kda_saved_size,
     kda_workspace_size,

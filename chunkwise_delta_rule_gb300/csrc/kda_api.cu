@@ -464,7 +464,8 @@ kda_status kda_device_status(const kda_problem* p, const void* ws, size_t ws_byt
     const size_t off = L.table - up(sizeof(int32_t));
     e = cudaMemcpy(word, static_cast<const char*>(ws) + off, sizeof(int32_t), cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return cuda_fail(e, "read error word");
-    if (*word) return fail(KDA_ERR_INVALID_ARG, "cu_seqlens was inconsistent and was clamped");
+    if (*word & 2) return fail(KDA_ERR_DEVICE_TIMEOUT, "a bounded device wait gave up; results are not valid");
+    if (*word & 1) return fail(KDA_ERR_INVALID_ARG, "cu_seqlens was inconsistent and was clamped");
     return KDA_OK;
 }
 

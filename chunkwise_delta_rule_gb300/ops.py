@@ -114,6 +114,16 @@ def _buffer(nbytes: int, device, given: Optional[torch.Tensor]) -> Optional[torc
     return torch.empty(nbytes, dtype=torch.uint8, device=device)
 
 
+def kda_device_status(p: Problem, workspace: torch.Tensor, stream=None):
+    """Synchronise and read the device error word a call left in `workspace`.
+    Returns (status, word); status 0 = OK."""
+    word = ctypes.c_int32(0)
+    nbytes = workspace.numel() * workspace.element_size()
+    st = _lib.load().kda_device_status(ctypes.byref(p.c), _ptr(workspace), nbytes, _stream(stream),
+                                       ctypes.byref(word))
+    return int(st), int(word.value)
+
+
 def kda_chunk_fwd(p: Problem, *, output_final_state: bool = True, workspace=None, saved=None,
                   stream=None):
     """Forward pass. Returns (o, ht or None, saved or None)."""

@@ -138,8 +138,10 @@ kda_status kda_chunk_bwd(const kda_problem *p, const void *dout, const float *dh
 kda_status kda_chunk_fwd_noalloc(const kda_problem *p, void *o, float *ht, kda_stream_t stream);
 
 /* Synchronises `stream` and reads the device error word a previous call left
- * in `ws` (bit 0: cu_seqlens inconsistent and clamped). Returns KDA_OK when
- * the word is clear. For diagnostics; the fast path never calls it. */
+ * in `ws` (bit 0: cu_seqlens inconsistent and clamped; bit 1: a bounded wait
+ * inside a kernel gave up, so that call's results are not valid). Returns
+ * KDA_OK when the word is clear, KDA_ERR_DEVICE_TIMEOUT if bit 1 is set, else
+ * KDA_ERR_INVALID_ARG. For diagnostics; the fast path never calls it. */
 kda_status kda_device_status(const kda_problem *p, const void *ws, size_t ws_bytes,
                              kda_stream_t stream, int32_t *word);
 

@@ -23,10 +23,14 @@ def gpu_run(case, policy=0, need_bwd=True):
     c = case.to("cuda")
     p = kda.make_problem(c.q, c.k, c.v, c.g, c.beta, gate=case.gate, scale=case.scale,
                          initial_state=c.h0, cu_seqlens=c.cu_seqlens, save_policy=policy)
-    o, ht, sv = kda.kda_chunk_fwd(p)
+    wsf = torch.empty(max(kda.kda_workspace_size(p, False), 1), dtype=torch.uint8, device="cuda")
+    o, ht, sv = kda.kda_chunk_fwd(p, workspace=wsf)
+    assert kda.kda_device_status(p, wsf) == (0, 0), "device error word set by the forward"
     out = dict(o=o, ht=ht)
     if need_bwd:
-        dq, dk, dv, dg, dbeta, dh0 = kda.kda_chunk_bwd(p, c.do, c.dht, saved=sv)
+        wsb = torch.empty(max(kda.kda_workspace_size(p, True), 1), dtype=torch.uint8, device="cuda")
+        dq, dk, dv, dg, dbeta, dh0 = kda.kda_chunk_bwd(p, c.do, c.dht, saved=sv, workspace=wsb)
+        assert kda.kda_device_status(p, wsb) == (0, 0), "device error word set by the backward"
         out.update(dq=dq, dk=dk, dv=dv, dg=dg, dbeta=dbeta, dh0=dh0)
     torch.cuda.synchronize()
     return out
