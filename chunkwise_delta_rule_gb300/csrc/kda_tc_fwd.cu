@@ -555,39 +555,35 @@ __device__ __forceinline__ void fscan_compute(const Shape& s, const float* __res
         if (it > 0) wait_one(&bar[1], (it - 1) & 1);   // the state update of chunk c-1
         tc::named_sync(NB_C, ST);
         // 1. S^T -> bf16 A operand of D1 = S^T W^T (TMEM), handed to the issuer
-        float sv[4][16];
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) tc::tmem_ld16(tl + kb + 16 * q4, sv[q4]);
-        tc::tmem_wait_ld();
 #pragma unroll
         for (int hq = 0; hq < 2; ++hq) {
+            float sv[2][16];
+            tc::tmem_ld16(tl + kb + 32 * hq, sv[0]);
+            tc::tmem_ld16(tl + kb + 32 * hq + 16, sv[1]);
+            tc::tmem_wait_ld();
             uint32_t pw[16];
 #pragma unroll
             for (int jj = 0; jj < 8; ++jj) {
-                pw[jj] = tc::pack_bf16(sv[2 * hq][2 * jj], sv[2 * hq][2 * jj + 1]);
-                pw[8 + jj] = tc::pack_bf16(sv[2 * hq + 1][2 * jj], sv[2 * hq + 1][2 * jj + 1]);
+                pw[jj] = tc::pack_bf16(sv[0][2 * jj], sv[0][2 * jj + 1]);
+                pw[8 + jj] = tc::pack_bf16(sv[1][2 * jj], sv[1][2 * jj + 1]);
             }
             tc::tmem_st16u(tl + T_AS + 64 * stage + kb / 2 + 16 * hq, pw);
         }
         tc::tmem_wait_st();
         tc::fence_before_sync();
         tc::named_sync(NB_AS, ST_ALL);
-        // 2. while D1 runs: the saved state, S^T <- S^T diag(lambda), the output of chunk c-1
+        // 2. while D1 runs: S^T <- S^T diag(lambda) (before the update MMAs accumulate)
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
             const int cb = kb + 16 * q4;
-            if (MODE & 2) tc::warp_store_t16_img(tst, sv[q4], f.HS + ch * D * D, D, cb, 32 * quad, lane);
+            float a[16];
+            tc::tmem_ld16(tl + cb, a);
+            tc::tmem_wait_ld();
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) sv[q4][jj] *= sLam[cb + jj];
-            tc::tmem_st16(tl + cb, sv[q4]);
+            for (int jj = 0; jj < 16; ++jj) a[jj] *= sLam[cb + jj];
+            tc::tmem_st16(tl + cb, a);
         }
         tc::tmem_wait_st();
-        if ((MODE & 1) && it > 0) {
-            wait_one(&bar[2], (it - 1) & 1);
-            fscan_store_out(tl + T_O + 64 * ((it - 1) & 1), lenp, tok0p, H, h, ib, quad, lane, tst, o);
-        }
-        lenp = len;
-        tok0p = tok0;
         // 3. R^T = U^T - D1 -> bf16 A operand (TMEM) of the state update and the output
         wait_one(&bar[0], it & 1);
         float rv[2][16];
@@ -608,17 +604,35 @@ __device__ __forceinline__ void fscan_compute(const Shape& s, const float* __res
         tc::tmem_wait_st();
         tc::fence_before_sync();
         tc::named_sync(NB_AR, ST_ALL);
+        // 4. while the state update runs: the saved S and R, the output of chunk c-1 (one output
+        //    barrier per TMEM buffer, so the commit of this chunk's output cannot be taken for it)
         if (MODE & 2) {
+            // the bf16 S^T of this chunk is still in its TMEM operand buffer
+#pragma unroll
+            for (int hq = 0; hq < 2; ++hq) {
+                float pv[16];
+                tc::tmem_ld16(tl + T_AS + 64 * stage + kb / 2 + 16 * hq, pv);
+                tc::tmem_wait_ld();
+                const uint32_t* pw = reinterpret_cast<const uint32_t*>(pv);
+                tc::warp_store_t16_img_packed(tst, pw, f.HS + ch * D * D, D, kb + 32 * hq, 32 * quad, lane);
+                tc::warp_store_t16_img_packed(tst, pw + 8, f.HS + ch * D * D, D, kb + 32 * hq + 16, 32 * quad, lane);
+            }
 #pragma unroll
             for (int cq = 0; cq < 32; cq += 16)
                 tc::warp_store_t16_img(tst, rv[cq / 16], f.R + ch * BT * D, BT, ib + cq, 32 * quad, lane);
         }
+        if ((MODE & 1) && it > 0) {
+            wait_one(&bar[2 + ((it - 1) & 1)], ((it - 1) >> 1) & 1);
+            fscan_store_out(tl + T_O + 64 * ((it - 1) & 1), lenp, tok0p, H, h, ib, quad, lane, tst, o);
+        }
+        lenp = len;
+        tok0p = tok0;
     }
     if (c1 > c0) {
         const int last = c1 - 1 - c0;
         wait_one(&bar[1], last & 1);
         if (MODE & 1) {
-            wait_one(&bar[2], last & 1);
+            wait_one(&bar[2 + (last & 1)], (last >> 1) & 1);
             fscan_store_out(tl + T_O + 64 * (last & 1), lenp, tok0p, H, h, ib, quad, lane, tst, o);
         }
     }
@@ -662,7 +676,11 @@ __device__ __forceinline__ void fscan_issue(const Shape& s, const Table& t, cons
             if (c + 1 < c1) {
                 // the other stage is free once every MMA of chunk c-1 has completed (a commit
                 // covers all earlier MMAs of the issuing thread)
-                if (it > 0 && !tc::mbar_wait(&bar[(MODE & 1) ? 2 : 1], (it - 1) & 1)) atomicOr(t.err, 2);
+                if (it > 0) {
+                    const bool done = (MODE & 1) ? tc::mbar_wait(&bar[2 + ((it - 1) & 1)], ((it - 1) >> 1) & 1)
+                                                 : tc::mbar_wait(&bar[1], (it - 1) & 1);
+                    if (!done) atomicOr(t.err, 2);
+                }
                 fscan_fill<MODE>(sb + OFF_STAGE + (stage ^ 1) * STG_BYTES, f, (size_t)(c + 1) * H + h,
                                  &full[stage ^ 1]);
                 ++filled;
@@ -685,7 +703,7 @@ __device__ __forceinline__ void fscan_issue(const Shape& s, const Table& t, cons
             for (int ks = 0; ks < 8; ++ks) tc::mma_bf16_ts_w(tO, aS + 8 * ks, tc::kstep_k(dQ, BT, ks), i64, ks > 0);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) tc::mma_bf16_ts_w(tO, aR + 8 * ks, tc::kstep_k(dA, BT, ks), i64, 1);
-            tc::mma_commit_w(&bar[2]);
+            tc::mma_commit_w(&bar[2 + stage]);
         }
     }
 }
@@ -697,9 +715,9 @@ __global__ void __launch_bounds__(ST_ALL, 1)
     extern __shared__ unsigned char smem_raw[];
     unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                            ~static_cast<uintptr_t>(1023));
-    uint64_t* bar = reinterpret_cast<uint64_t*>(base + OFF_BAR);   // D1, state update, output
-    uint64_t* full = bar + 3;                                        // operand stages 0, 1
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 5);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(base + OFF_BAR);   // D1, state update, output (x2)
+    uint64_t* full = bar + 4;                                        // operand stages 0, 1
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 6);
     const uint32_t sb = tc::smem_u32(base);
     const int nseq = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5;
     const int c0 = t.seq_chunk0[nseq], c1 = t.seq_chunk0[nseq + 1];
@@ -707,7 +725,7 @@ __global__ void __launch_bounds__(ST_ALL, 1)
     int filled = 0, waited = 0;   // bulk fills issued / consumed (issuer lane 0)
 
     if (issuer && (tid & 31) == 0) {
-        for (int i = 0; i < 5; ++i) tc::mbar_init(&bar[i], 1);
+        for (int i = 0; i < 6; ++i) tc::mbar_init(&bar[i], 1);
         tc::fence_mbar_init();
         if (c0 < c1) {
             fscan_fill<MODE>(sb + OFF_STAGE, f, (size_t)c0 * s.H + h, &full[0]);
