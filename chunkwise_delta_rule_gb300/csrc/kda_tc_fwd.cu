@@ -442,9 +442,8 @@ constexpr int NB_C = 3;            //                compute warps only
 
 // Shared-memory map (bytes from the 1024-aligned base): the B operands only.
 constexpr int OFF_STAGE = 0;                 // two stages
-constexpr int STG_W = 0;                     // W   [64][128]  16 KB
-constexpr int STG_KG = 16384;                // F   [64][128]  16 KB (read MN-major)
-constexpr int STG_QG = 32768;                // Q_g [64][128]  16 KB
+constexpr int STG_WQ = 0;                    // [W ; Q_g] as one K-major [128][128] tile  32 KB
+constexpr int STG_KG = 32768;                // F   [64][128]  16 KB (read MN-major)
 constexpr int STG_AQ = 49152;                // C_q [64][64]    8 KB
 constexpr int STG_BYTES = 57344;
 constexpr int OFF_LAM = OFF_STAGE + 2 * STG_BYTES;   // lambda [128] fp32
@@ -453,12 +452,13 @@ constexpr int OFF_BAR = OFF_TST + 8 * 1280;
 constexpr int SCAN_SMEM = OFF_BAR + 64 + 1024;
 static_assert(SCAN_SMEM <= 232448, "scan shared memory above the per-block limit");
 
-// TMEM columns: S^T fp32 [0,128), D1 = S^T W^T [128,192), O^T double buffer [192,320);
-// the bf16 A operands S^T (64 columns) and R^T (32 columns), double-buffered so
-// that the output MMAs of chunk c, issued after its state update, may still
-// read them while chunk c+1 runs: [320,448) and [448,512). The MMAs then read
+// TMEM columns: S^T fp32 [0,128); two buffers [D1 | O^T] of 128 columns at
+// [128,256) and [256,384), where one N = 128 pass S^T [W ; Q_g]^T gives D1 = S^T W^T
+// and the first output term, and R^T C_q^T is added to the output half after
+// the state update (read back during the next chunk); the bf16 A operands
+// S^T (64 columns) at [384,448) and R^T (32 columns) at [448,480). The MMAs read
 // only their B operands from shared memory.
-constexpr int T_D1 = 128, T_O = 192, T_AS = 320, T_AR = 448;
+constexpr int T_DO = 128, T_AS = 384, T_AR = 448;
 
 // Stages the operand tiles of one chunk (stored as tile images) with bulk
 // copies; one thread; completion arrives on `full` as transaction bytes.
@@ -466,10 +466,15 @@ template <int MODE>
 __device__ __forceinline__ void fscan_fill(uint32_t stg, const FwdTC& f, size_t ch, uint64_t* full) {
     constexpr uint32_t TILE = BT * D * 2, TQ = BT * BT * 2;
     tc::mbar_arrive_expect_tx(full, (MODE & 1) ? 3 * TILE + TQ : 2 * TILE);
-    tc::bulk_g2s(stg + STG_W, f.W + ch * BT * D, TILE, full);
+    // W in rows 0..63 and Q_g in rows 64..127 of each 64-column atom block
+    const unsigned char* w = reinterpret_cast<const unsigned char*>(f.W + ch * BT * D);
+    tc::bulk_g2s(stg + STG_WQ, w, TILE / 2, full);
+    tc::bulk_g2s(stg + STG_WQ + 2 * BT * 128, w + TILE / 2, TILE / 2, full);
     tc::bulk_g2s(stg + STG_KG, f.KG + ch * BT * D, TILE, full);
     if (MODE & 1) {
-        tc::bulk_g2s(stg + STG_QG, f.QG + ch * BT * D, TILE, full);
+        const unsigned char* qg = reinterpret_cast<const unsigned char*>(f.QG + ch * BT * D);
+        tc::bulk_g2s(stg + STG_WQ + BT * 128, qg, TILE / 2, full);
+        tc::bulk_g2s(stg + STG_WQ + 3 * BT * 128, qg + TILE / 2, TILE / 2, full);
         tc::bulk_g2s(stg + STG_AQ, f.AQK + ch * BT * BT, TQ, full);
     }
 }
@@ -567,7 +572,7 @@ __device__ __forceinline__ void fscan_compute(const Shape& s, const float* __res
                 pw[jj] = tc::pack_bf16(sv[0][2 * jj], sv[0][2 * jj + 1]);
                 pw[8 + jj] = tc::pack_bf16(sv[1][2 * jj], sv[1][2 * jj + 1]);
             }
-            tc::tmem_st16u(tl + T_AS + 64 * stage + kb / 2 + 16 * hq, pw);
+            tc::tmem_st16u(tl + T_AS + kb / 2 + 16 * hq, pw);
         }
         tc::tmem_wait_st();
         tc::fence_before_sync();
@@ -587,8 +592,8 @@ __device__ __forceinline__ void fscan_compute(const Shape& s, const float* __res
         // 3. R^T = U^T - D1 -> bf16 A operand (TMEM) of the state update and the output
         wait_one(&bar[0], it & 1);
         float rv[2][16];
-        tc::tmem_ld16(tl + T_D1 + ib, rv[0]);
-        tc::tmem_ld16(tl + T_D1 + ib + 16, rv[1]);
+        tc::tmem_ld16(tl + T_DO + 128 * stage + ib, rv[0]);
+        tc::tmem_ld16(tl + T_DO + 128 * stage + ib + 16, rv[1]);
         tc::tmem_wait_ld();
         {
             uint32_t pw[16];
@@ -599,7 +604,7 @@ __device__ __forceinline__ void fscan_compute(const Shape& s, const float* __res
 #pragma unroll
                 for (int jj = 0; jj < 8; ++jj) pw[8 * cq + jj] = tc::pack_bf16(rv[cq][2 * jj], rv[cq][2 * jj + 1]);
             }
-            tc::tmem_st16u(tl + T_AR + 32 * stage + ib / 2, pw);
+            tc::tmem_st16u(tl + T_AR + ib / 2, pw);
         }
         tc::tmem_wait_st();
         tc::fence_before_sync();
@@ -611,7 +616,7 @@ __device__ __forceinline__ void fscan_compute(const Shape& s, const float* __res
 #pragma unroll
             for (int hq = 0; hq < 2; ++hq) {
                 float pv[16];
-                tc::tmem_ld16(tl + T_AS + 64 * stage + kb / 2 + 16 * hq, pv);
+                tc::tmem_ld16(tl + T_AS + kb / 2 + 16 * hq, pv);
                 tc::tmem_wait_ld();
                 const uint32_t* pw = reinterpret_cast<const uint32_t*>(pv);
                 tc::warp_store_t16_img_packed(tst, pw, f.HS + ch * D * D, D, kb + 32 * hq, 32 * quad, lane);
@@ -623,7 +628,7 @@ __device__ __forceinline__ void fscan_compute(const Shape& s, const float* __res
         }
         if ((MODE & 1) && it > 0) {
             wait_one(&bar[2 + ((it - 1) & 1)], ((it - 1) >> 1) & 1);
-            fscan_store_out(tl + T_O + 64 * ((it - 1) & 1), lenp, tok0p, H, h, ib, quad, lane, tst, o);
+            fscan_store_out(tl + T_DO + 128 * ((it - 1) & 1) + 64, lenp, tok0p, H, h, ib, quad, lane, tst, o);
         }
         lenp = len;
         tok0p = tok0;
@@ -633,7 +638,7 @@ __device__ __forceinline__ void fscan_compute(const Shape& s, const float* __res
         wait_one(&bar[1], last & 1);
         if (MODE & 1) {
             wait_one(&bar[2 + (last & 1)], (last >> 1) & 1);
-            fscan_store_out(tl + T_O + 64 * (last & 1), lenp, tok0p, H, h, ib, quad, lane, tst, o);
+            fscan_store_out(tl + T_DO + 128 * (last & 1) + 64, lenp, tok0p, H, h, ib, quad, lane, tst, o);
         }
     }
     if (ok && ht) {
@@ -656,19 +661,21 @@ __device__ __forceinline__ void fscan_issue(const Shape& s, const Table& t, cons
                                             int& filled, int& waited) {
     const int lane = threadIdx.x & 31;
     const int H = s.H;
-    const uint32_t i64 = tc::idesc_bf16(128, 64), i128m = tc::idesc_bf16_bmn(128, 128);
+    const uint32_t i1 = tc::idesc_bf16(128, (MODE & 1) ? 128 : 64), i64 = tc::idesc_bf16(128, 64),
+                   i128m = tc::idesc_bf16_bmn(128, 128);
+    const uint32_t aS = tb + T_AS, aR = tb + T_AR;   // A operands in TMEM
     for (int c = c0; c < c1; ++c) {
         const int it = c - c0, stage = it & 1;
         const uint32_t stg = sb + OFF_STAGE + stage * STG_BYTES;
-        const uint32_t aS = tb + T_AS + 64 * stage, aR = tb + T_AR + 32 * stage;   // A operands in TMEM
+        const uint32_t tD = tb + T_DO + 128 * stage;
         tc::named_sync(NB_AS, ST_ALL);
         tc::fence_after_sync();
         if (!tc::mbar_wait(&full[stage], (it >> 1) & 1) && lane == 0) atomicOr(t.err, 2);
         {
-            const uint64_t dW = tc::sdesc(stg + STG_W);
+            // [D1 | O] = S^T [W ; Q_g]^T (D1 alone without the output)
+            const uint64_t dWQ = tc::sdesc(stg + STG_WQ);
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks)
-                tc::mma_bf16_ts_w(tb + T_D1, aS + 8 * ks, tc::kstep_k(dW, BT, ks), i64, ks > 0);
+            for (int ks = 0; ks < 8; ++ks) tc::mma_bf16_ts_w(tD, aS + 8 * ks, tc::kstep_k(dWQ, 2 * BT, ks), i1, ks > 0);
             tc::mma_commit_w(&bar[0]);
         }
         if (lane == 0) {
@@ -689,7 +696,7 @@ __device__ __forceinline__ void fscan_issue(const Shape& s, const Table& t, cons
         __syncwarp();
         tc::named_sync(NB_AR, ST_ALL);
         tc::fence_after_sync();
-        // S^T += R^T F first (it gates the next chunk), then O^T = S^T Q_g^T + R^T C_q^T
+        // S^T += R^T F first (it gates the next chunk), then O^T += R^T C_q^T
         {
             const uint64_t dF = tc::sdesc_mn(stg + STG_KG, BT * 128, 0);
 #pragma unroll
@@ -697,12 +704,9 @@ __device__ __forceinline__ void fscan_issue(const Shape& s, const Table& t, cons
             tc::mma_commit_w(&bar[1]);
         }
         if (MODE & 1) {
-            const uint32_t tO = tb + T_O + 64 * stage;
-            const uint64_t dQ = tc::sdesc(stg + STG_QG), dA = tc::sdesc(stg + STG_AQ);
+            const uint64_t dA = tc::sdesc(stg + STG_AQ);
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) tc::mma_bf16_ts_w(tO, aS + 8 * ks, tc::kstep_k(dQ, BT, ks), i64, ks > 0);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) tc::mma_bf16_ts_w(tO, aR + 8 * ks, tc::kstep_k(dA, BT, ks), i64, 1);
+            for (int ks = 0; ks < 4; ++ks) tc::mma_bf16_ts_w(tD + 64, aR + 8 * ks, tc::kstep_k(dA, BT, ks), i64, 1);
             tc::mma_commit_w(&bar[2 + stage]);
         }
     }
