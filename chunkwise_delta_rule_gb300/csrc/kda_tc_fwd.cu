@@ -446,9 +446,11 @@ constexpr int STG_WQ = 0;                    // [W ; Q_g] as one K-major [128][1
 constexpr int STG_KG = 32768;                // F   [64][128]  16 KB (read MN-major)
 constexpr int STG_AQ = 49152;                // C_q [64][64]    8 KB
 constexpr int STG_BYTES = 57344;
-constexpr int OFF_LAM = OFF_STAGE + 2 * STG_BYTES;   // lambda [128] fp32
+constexpr int OFF_OST = OFF_STAGE + 2 * STG_BYTES;   // output staging, 2 x [64][128] bf16 tile images, 32 KB
+constexpr int OFF_LAM = OFF_OST + 2 * BT * D * 2;     // lambda [128] fp32
 constexpr int OFF_TST = OFF_LAM + 512;                 // per-warp transpose staging, 8 x 1280 B
 constexpr int OFF_BAR = OFF_TST + 8 * 1280;
+static_assert(OFF_OST % 1024 == 0, "swizzled TMA stores need 1024-byte aligned tiles");
 constexpr int SCAN_SMEM = OFF_BAR + 64 + 1024;
 static_assert(SCAN_SMEM <= 232448, "scan shared memory above the per-block limit");
 
@@ -479,10 +481,20 @@ __device__ __forceinline__ void fscan_fill(uint32_t stg, const FwdTC& f, size_t 
     }
 }
 
-// Rows [ib, ib+32) of the output of a chunk (len tokens from tok0) from O^T in
-// TMEM (this thread: value column vcol).
-__device__ __forceinline__ void fscan_store_out(uint32_t tl_o, int len, int tok0, int H, int h, int ib,
-                                                int quad, int lane, bf16* tst, bf16* __restrict__ o) {
+// The output of a full chunk from its staging tile (a [64][128] tile image) to
+// HBM: two TMA box stores, one per 64-column atom block (lane 0 of the caller).
+__device__ __forceinline__ void fscan_tma_out(const CUtensorMap* tmo, uint32_t ost, int tok0, int h, int lane) {
+    if (lane == 0) {
+        tc::tma_store3(tmo, 0, h, tok0, ost);
+        tc::tma_store3(tmo, 64, h, tok0, ost + BT * 128);
+        tc::bulk_commit();
+    }
+}
+
+// A tail chunk's output rows [ib, ib+32) straight from O^T in TMEM (this thread:
+// value column vcol), rows >= len skipped.
+__device__ __forceinline__ void fscan_store_tail(uint32_t tl_o, int len, int tok0, int H, int h, int ib, int quad,
+                                                 int lane, bf16* tst, bf16* __restrict__ o) {
     float ov[2][16];
     tc::tmem_ld16(tl_o + ib, ov[0]);
     tc::tmem_ld16(tl_o + ib + 16, ov[1]);
@@ -496,13 +508,16 @@ __device__ __forceinline__ void fscan_store_out(uint32_t tl_o, int len, int tok0
     }
 }
 
-// Small per-chunk inputs of a compute thread, loaded a chunk ahead: G at the
-// chunk end (threads < D) and the chunk's extent.
-__device__ __forceinline__ void fscan_load_next(const FwdTC& f, const Table& t, int c, int H, int h, int tid,
-                                                float& gln, int& len, int& tok0) {
-    if (tid < D) gln = __ldg(f.GL + ((size_t)c * H + h) * D + tid);
-    len = __ldg(t.chunk_len + c);
-    tok0 = __ldg(t.chunk_tok0 + c);
+// A full chunk's output from O^T in TMEM into its staging tile image (rows
+// [ib, ib+32) of value column vcol), then made visible to the TMA store.
+__device__ __forceinline__ void fscan_stage_out(uint32_t tl_o, bf16* ost, int ib, int vcol) {
+    float ov[2][16];
+    tc::tmem_ld16(tl_o + ib, ov[0]);
+    tc::tmem_ld16(tl_o + ib + 16, ov[1]);
+    tc::tmem_wait_ld();
+#pragma unroll
+    for (int j = 0; j < 32; ++j) ost[tile_el(BT, ib + j, vcol)] = __float2bfloat16_rn(ov[j >> 4][j & 15]);
+    tc::fence_async_smem();
 }
 
 // Compute warps: every per-element pass over S^T, D1, R^T and O^T. The work
@@ -543,9 +558,10 @@ __device__ __forceinline__ void fscan_compute(const Shape& s, const float* __res
         }
         tc::fence_after_sync();
     };
+    // G at the chunk end (threads < D), loaded a chunk ahead; the previous chunk's extent
     float gln = 0.f;
-    int lenn = 0, tok0n = 0, lenp = 0, tok0p = 0;
-    if (c0 < c1) fscan_load_next(f, t, c0, H, h, tid, gln, lenn, tok0n);
+    if (c0 < c1 && tid < D) gln = __ldg(f.GL + ((size_t)c0 * H + h) * D + tid);
+    int lenp = 0, tok0p = 0;
     for (int c = c0; c < c1; ++c) {
         const int it = c - c0, stage = it & 1;
         const size_t ch = (size_t)c * H + h;
@@ -554,9 +570,8 @@ __device__ __forceinline__ void fscan_compute(const Shape& s, const float* __res
         const float* U = f.U + ch * BT * D + (size_t)ib * D + vcol;
 #pragma unroll
         for (int i = 0; i < 32; ++i) u[i] = __ldg(U + (size_t)i * D);
-        const int len = lenn, tok0 = tok0n;
         if (tid < D) sLam[tid] = exp2f(gln);
-        if (c + 1 < c1) fscan_load_next(f, t, c + 1, H, h, tid, gln, lenn, tok0n);
+        if (c + 1 < c1 && tid < D) gln = __ldg(f.GL + (ch + H) * D + tid);
         if (it > 0) wait_one(&bar[1], (it - 1) & 1);   // the state update of chunk c-1
         tc::named_sync(NB_C, ST);
         // 1. S^T -> bf16 A operand of D1 = S^T W^T (TMEM), handed to the issuer
@@ -627,18 +642,29 @@ __device__ __forceinline__ void fscan_compute(const Shape& s, const float* __res
                 tc::warp_store_t16_img(tst, rv[cq / 16], f.R + ch * BT * D, BT, ib + cq, 32 * quad, lane);
         }
         if ((MODE & 1) && it > 0) {
+            // output of chunk c-1: a full chunk goes to staging tile (it-1)&1 (stored by the
+            // issuer after the next hand-over), a tail chunk straight to HBM
             wait_one(&bar[2 + ((it - 1) & 1)], ((it - 1) >> 1) & 1);
-            fscan_store_out(tl + T_DO + 128 * ((it - 1) & 1) + 64, lenp, tok0p, H, h, ib, quad, lane, tst, o);
+            const uint32_t to = tl + T_DO + 128 * ((it - 1) & 1) + 64;
+            if (lenp == BT)
+                fscan_stage_out(to, reinterpret_cast<bf16*>(base + OFF_OST) + ((it - 1) & 1) * BT * D, ib, vcol);
+            else
+                fscan_store_tail(to, lenp, tok0p, H, h, ib, quad, lane, tst, o);
         }
-        lenp = len;
-        tok0p = tok0;
+        lenp = __ldg(t.chunk_len + c);
+        tok0p = __ldg(t.chunk_tok0 + c);
     }
     if (c1 > c0) {
         const int last = c1 - 1 - c0;
         wait_one(&bar[1], last & 1);
         if (MODE & 1) {
+            // the last output: staging tile last&1 (stored by the issuer at the end) or HBM
             wait_one(&bar[2 + (last & 1)], (last >> 1) & 1);
-            fscan_store_out(tl + T_DO + 128 * (last & 1) + 64, lenp, tok0p, H, h, ib, quad, lane, tst, o);
+            const uint32_t to = tl + T_DO + 128 * (last & 1) + 64;
+            if (lenp == BT)
+                fscan_stage_out(to, reinterpret_cast<bf16*>(base + OFF_OST) + (last & 1) * BT * D, ib, vcol);
+            else
+                fscan_store_tail(to, lenp, tok0p, H, h, ib, quad, lane, tst, o);
         }
     }
     if (ok && ht) {
@@ -656,9 +682,9 @@ __device__ __forceinline__ void fscan_compute(const Shape& s, const float* __res
 // Issuer warp: bulk fills of the operand stages (lane 0) and every MMA (the
 // whole warp with warp-uniform descriptors, one elected lane issuing).
 template <int MODE>
-__device__ __forceinline__ void fscan_issue(const Shape& s, const Table& t, const FwdTC& f, uint32_t sb,
-                                            uint64_t* bar, uint64_t* full, uint32_t tb, int h, int c0, int c1,
-                                            int& filled, int& waited) {
+__device__ __forceinline__ void fscan_issue(const Shape& s, const Table& t, const FwdTC& f, const CUtensorMap* tmo,
+                                            uint32_t sb, uint64_t* bar, uint64_t* full, uint32_t tb, int h, int c0,
+                                            int c1, int& pl, int& pt, int& filled, int& waited) {
     const int lane = threadIdx.x & 31;
     const int H = s.H;
     const uint32_t i1 = tc::idesc_bf16(128, (MODE & 1) ? 128 : 64), i64 = tc::idesc_bf16(128, 64),
@@ -693,6 +719,15 @@ __device__ __forceinline__ void fscan_issue(const Shape& s, const Table& t, cons
                 ++filled;
             }
         }
+        // the output of chunk c-2 (a full chunk), staged by the compute warps during chunk c-1
+        if ((MODE & 1) && it >= 2 && pl == BT) fscan_tma_out(tmo, sb + OFF_OST + (it & 1) * BT * D * 2, pt, h, lane);
+        if ((MODE & 1) && it >= 1) {   // extent of chunk c-1, whose output is stored next iteration
+            pl = __ldg(t.chunk_len + c - 1);
+            pt = __ldg(t.chunk_tok0 + c - 1);
+        }
+        // the staging tile stored during chunk c-1 is rewritten after this hand-over; the one
+        // stored just now may still be read (it is rewritten during chunk c+1)
+        if ((MODE & 1) && lane == 0) tc::bulk_wait_read_prev();
         __syncwarp();
         tc::named_sync(NB_AR, ST_ALL);
         tc::fence_after_sync();
@@ -714,8 +749,8 @@ __device__ __forceinline__ void fscan_issue(const Shape& s, const Table& t, cons
 
 template <int MODE>
 __global__ void __launch_bounds__(ST_ALL, 1)
-    k_fwd_scan_tc(Shape s, const float* __restrict__ h0, Table t, FwdTC f, bf16* __restrict__ o,
-                  float* __restrict__ ht) {
+    k_fwd_scan_tc(Shape s, const __grid_constant__ CUtensorMap tmo, const float* __restrict__ h0, Table t, FwdTC f,
+                  bf16* __restrict__ o, float* __restrict__ ht) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                            ~static_cast<uintptr_t>(1023));
@@ -727,6 +762,7 @@ __global__ void __launch_bounds__(ST_ALL, 1)
     const int c0 = t.seq_chunk0[nseq], c1 = t.seq_chunk0[nseq + 1];
     const bool issuer = warp == ST / 32;
     int filled = 0, waited = 0;   // bulk fills issued / consumed (issuer lane 0)
+    int pl = 0, pt = 0;           // extent of the chunk whose output is staged but not yet stored
 
     if (issuer && (tid & 31) == 0) {
         for (int i = 0; i < 6; ++i) tc::mbar_init(&bar[i], 1);
@@ -745,7 +781,7 @@ __global__ void __launch_bounds__(ST_ALL, 1)
     tc::fence_after_sync();
     const uint32_t tb = *tslot;
     if (issuer)
-        fscan_issue<MODE>(s, t, f, sb, bar, full, tb, h, c0, c1, filled, waited);
+        fscan_issue<MODE>(s, t, f, &tmo, sb, bar, full, tb, h, c0, c1, pl, pt, filled, waited);
     else
         fscan_compute<MODE>(s, h0, t, f, o, ht, base, bar, tb, nseq, h, c0, c1);
     // a bulk fill still in flight (only after a timeout) lands before the CTA leaves
@@ -753,6 +789,14 @@ __global__ void __launch_bounds__(ST_ALL, 1)
         for (; waited < filled; ++waited) tc::mbar_wait(&full[waited & 1], (waited >> 1) & 1);
     tc::fence_before_sync();
     __syncthreads();
+    // the last two outputs (staged after the issuer's loop ended)
+    if ((MODE & 1) && issuer && c1 > c0) {
+        const int last = c1 - 1 - c0, lane = tid & 31;
+        if (last >= 1 && pl == BT) fscan_tma_out(&tmo, sb + OFF_OST + ((last - 1) & 1) * BT * D * 2, pt, h, lane);
+        if (t.chunk_len[c1 - 1] == BT)
+            fscan_tma_out(&tmo, sb + OFF_OST + (last & 1) * BT * D * 2, t.chunk_tok0[c1 - 1], h, lane);
+        if (lane == 0) tc::bulk_wait_all();
+    }
     if (warp == 0) tc::tmem_dealloc(tb, 512);
 }
 
@@ -775,8 +819,11 @@ template <int MODE>
 cudaError_t run_scan(const Shape& s, const float* h0, Table t, FwdTC f, void* o, float* ht, cudaStream_t st) {
     cudaError_t e = set_smem_once<k_fwd_scan_tc<MODE>>(SCAN_SMEM);
     if (e != cudaSuccess) return e;
+    CUtensorMap mo;
+    memset(&mo, 0, sizeof(mo));
+    if ((MODE & 1) && !tmap_rows_bf16(&mo, o, s.Ttot, s.H, D)) return cudaErrorInvalidValue;
     dim3 grid(s.N, s.H);
-    k_fwd_scan_tc<MODE><<<grid, ST_ALL, SCAN_SMEM, st>>>(s, h0, t, f, (bf16*)o, ht);
+    k_fwd_scan_tc<MODE><<<grid, ST_ALL, SCAN_SMEM, st>>>(s, mo, h0, t, f, (bf16*)o, ht);
     return cudaGetLastError();
 }
 

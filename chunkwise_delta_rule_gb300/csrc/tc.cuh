@@ -140,6 +140,32 @@ __device__ __forceinline__ void tma_load3(uint32_t dst, const CUtensorMap* map, 
         : "memory");
 }
 
+// TMA store of one box of a 3-D tensor map at (x, y, z) from shared memory
+// (laid out as the map's swizzle expects), in this thread's bulk group. The
+// box is written whole: use it only where every row of the box is the caller's.
+__device__ __forceinline__ void tma_store3(const CUtensorMap* map, int x, int y, int z, uint32_t src) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z), "r"(src)
+                 : "memory");
+}
+
+// Bulk copy shared -> global (no tensor map) in this thread's bulk group; both
+// addresses 16-byte aligned, bytes a multiple of 16. commit / wait_read /
+// wait_all manage the thread's groups (wait_read: the shared source may be
+// reused; wait_all: the writes are complete).
+__device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// All but the most recent group have finished reading their shared source.
+__device__ __forceinline__ void bulk_wait_read_prev() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // Named CTA barrier (id 1..15; 0 is __syncthreads): waits for `count` threads
 // (a multiple of 32).
 __device__ __forceinline__ void named_sync(int id, int count) {
