@@ -393,6 +393,8 @@ __global__ void __launch_bounds__(CT, 1)
     const int tok0 = t.chunk_tok0[c];
     const float scale = s.scale;
 
+    // beta (read now, stored to shared memory once the loads below are in flight)
+    const float beta_r = (tid < BT && tid < n) ? bfx(beta + (size_t)(tok0 + tid) * H + h) : 0.f;
     // token-major inputs by TMA: k, q (SW128 rows), dO (rows 0..63 of the [dO ; P] tile), g (fp32
     // rows). Rows past the chunk end hold the following tokens (or zeros past the tensor); every
     // use below either masks them or only reaches rows that are never stored.
@@ -441,7 +443,6 @@ __global__ void __launch_bounds__(CT, 1)
             *reinterpret_cast<float4*>(sA + r * D + c4) = make_float4(x, x, x, x);
         }
     }
-    if (tid < BT) sBeta[tid] = (tid < n) ? bfx(beta + (size_t)(tok0 + tid) * H + h) : 0.f;
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
@@ -471,6 +472,7 @@ __global__ void __launch_bounds__(CT, 1)
     }
     // while the MMAs run: cumsum (4 segments of 16 rows per feature), anchors, alpha tile;
     // rowsum(S .* S+bar) and <v_i, P_i>, dv = beta P from the staged tiles
+    if (tid < BT) sBeta[tid] = beta_r;   // visible after the barrier inside the cumsum
     {
         const int col = tid >> 2, seg = tid & 3;
         float x[16];
@@ -577,32 +579,33 @@ __global__ void __launch_bounds__(CT, 1)
             tc::tmem_st16(ta, a);
             tc::tmem_wait_st();
         }
-        // (K zeta)^T: rows = key k, K = token j (zeta = 1/alpha; unit without a per-channel gate)
-        for (int idx = tid; idx < D * 16; idx += CT) {
-            const int kr = idx & (D - 1), cc = idx >> 7;
-            float4 val;
-            float* pv = reinterpret_cast<float*>(&val);
+        // (K zeta)^T (rows = key k, K = token j; zeta = 1/alpha, unit without a per-channel gate) and
+        // [E_alpha^T | Q_alpha^T] (rows = key k, K = token: E part, then Q part), one pass: each
+        // thread owns key kr and four groups of four tokens; rows past the chunk end are zero
+        {
+            const int kr = tid & (D - 1), kch = (kr >> 3) & 7;
+            const uint32_t kbase = (uint32_t)((kr >> 6) * BT * 128 + (kr & 7) * 2);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int j = 4 * cc + e;
-                const float kv = (j < n) ? ldsw(sK, j, kr) : 0.f;
-                pv[e] = (GATE == 2) ? kv * tc::rcp_approx(sA[aidx(j, kr)]) : kv;
-            }
-            *reinterpret_cast<float4*>(base + X_KZ + tc::sw128_off(D, kr, cc * 16)) = val;
-        }
-        // [E_alpha^T | Q_alpha^T]: rows = key k, K = token (E part, then Q part)
-        for (int idx = tid; idx < D * 32; idx += CT) {
-            const int kr = idx & (D - 1), cc = idx >> 7;
-            float4 val;
-            float* pv = reinterpret_cast<float*>(&val);
+            for (int u = 0; u < 4; ++u) {
+                const int g = (tid >> 7) + 4 * u;   // tokens 4g .. 4g+3
+                float kz[4], ea[4], qa[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int kk = 4 * cc + e;
-                const int j = kk & (BT - 1);
-                const float al = (GATE == 2) ? sA[aidx(j, kr)] : 1.f;
-                pv[e] = (j >= n) ? 0.f : (kk < BT) ? sBeta[j] * ldsw(sK, j, kr) * al : scale * ldsw(sQ, j, kr) * al;
+                for (int e = 0; e < 4; ++e) {
+                    const int j = 4 * g + e;
+                    const uint32_t off = kbase + j * 128 + ((kch ^ (j & 7)) << 4);
+                    const float kv = __bfloat162float(*reinterpret_cast<const bf16*>(sK + off));
+                    const float qv = __bfloat162float(*reinterpret_cast<const bf16*>(sQ + off));
+                    const float al = (GATE == 2) ? sA[aidx(j, kr)] : 1.f;
+                    const bool in = j < n;
+                    kz[e] = in ? ((GATE == 2) ? kv * tc::rcp_approx(al) : kv) : 0.f;
+                    ea[e] = in ? sBeta[j] * kv * al : 0.f;
+                    qa[e] = in ? scale * qv * al : 0.f;
+                }
+                *reinterpret_cast<float4*>(base + X_KZ + tc::sw128_off(D, kr, g * 16)) = make_float4(kz[0], kz[1], kz[2], kz[3]);
+                *reinterpret_cast<float4*>(base + X_EQ + tc::sw128_off(D, kr, g * 16)) = make_float4(ea[0], ea[1], ea[2], ea[3]);
+                *reinterpret_cast<float4*>(base + X_EQ + tc::sw128_off(D, kr, (16 + g) * 16)) =
+                    make_float4(qa[0], qa[1], qa[2], qa[3]);
             }
-            *reinterpret_cast<float4*>(base + X_EQ + tc::sw128_off(D, kr, cc * 16)) = val;
         }
         tc::fence_async_smem();
         tc::fence_before_sync();
