@@ -60,8 +60,8 @@ constexpr int LW = D + 8;   // row stride (bf16) of the staged W tile
 //  2. the 16 x 16 blocks below them, A_10 = -A_11 (L_10 A_00) (and 3, 2);
 //  3. the lower-left 32 x 32 block the same way from the 32 x 32 halves.
 // Every block row/column product is a plain fp32 sum; 256 threads.
-constexpr int LA = BT + 1;   // row stride of sAi
-constexpr int LT1 = 17, LT2 = 33;
+constexpr int LA = BT + 4;   // row stride of sAi (16-byte aligned rows for vector loads)
+constexpr int LT1 = 18, LT2 = 36;
 __device__ __forceinline__ void inverse_blocked(const float* __restrict__ sLt, float* __restrict__ sAi,
                                                 float* __restrict__ sT, int tid, int warp, int lane) {
     if (warp < 4) {
@@ -75,70 +75,75 @@ __device__ __forceinline__ void inverse_blocked(const float* __restrict__ sLt, f
 #pragma unroll
             for (int cc = 0; cc < 8; ++cc) x[cc] = fmaf(-l, __shfl_sync(0xffffffffu, x[cc], (lane & 16) | m), x[cc]);
         }
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc) sAi[(b0 + r) * LA + b0 + 8 * ch + cc] = x[cc];
+        *reinterpret_cast<float4*>(sAi + (b0 + r) * LA + b0 + 8 * ch) = make_float4(x[0], x[1], x[2], x[3]);
+        *reinterpret_cast<float4*>(sAi + (b0 + r) * LA + b0 + 8 * ch + 4) = make_float4(x[4], x[5], x[6], x[7]);
     } else {
         // zero blocks above the diagonal
-        for (int idx = tid - 128; idx < 6 * 256; idx += 128) {
-            const int blk = idx >> 8, e = idx & 255;
+        for (int idx = tid - 128; idx < 6 * 64; idx += 128) {
+            const int blk = idx >> 6, e = idx & 63;
             const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
             const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-            sAi[(16 * bi + (e >> 4)) * LA + 16 * bj + (e & 15)] = 0.f;
+            *reinterpret_cast<float4*>(sAi + (16 * bi + (e >> 2)) * LA + 16 * bj + 4 * (e & 3)) =
+                make_float4(0.f, 0.f, 0.f, 0.f);
         }
     }
     __syncthreads();
     {   // T = L_10 A_00 (pair 0) and L_32 A_22 (pair 1); two outputs per thread
         const int pr = tid >> 7, r = (tid >> 3) & 15, c = (tid & 7) * 2;
         const int bi = 32 * pr + 16, bj = 32 * pr;
-        float t0 = 0.f, t1 = 0.f;
+        float2 t = make_float2(0.f, 0.f);
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
             const float l = sLt[(bj + k) * BT + bi + r];
-            t0 = fmaf(l, sAi[(bj + k) * LA + bj + c], t0);
-            t1 = fmaf(l, sAi[(bj + k) * LA + bj + c + 1], t1);
+            const float2 a = *reinterpret_cast<const float2*>(sAi + (bj + k) * LA + bj + c);
+            t.x = fmaf(l, a.x, t.x);
+            t.y = fmaf(l, a.y, t.y);
         }
-        sT[(16 * pr + r) * LT1 + c] = t0;
-        sT[(16 * pr + r) * LT1 + c + 1] = t1;
+        *reinterpret_cast<float2*>(sT + (16 * pr + r) * LT1 + c) = t;
     }
     __syncthreads();
     {   // A_10 = -A_11 T
         const int pr = tid >> 7, r = (tid >> 3) & 15, c = (tid & 7) * 2;
         const int bi = 32 * pr + 16, bj = 32 * pr;
-        float a0 = 0.f, a1 = 0.f;
+        float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
             const float x = sAi[(bi + r) * LA + bi + k];
-            a0 = fmaf(x, sT[(16 * pr + k) * LT1 + c], a0);
-            a1 = fmaf(x, sT[(16 * pr + k) * LT1 + c + 1], a1);
+            const float2 tt = *reinterpret_cast<const float2*>(sT + (16 * pr + k) * LT1 + c);
+            acc.x = fmaf(x, tt.x, acc.x);
+            acc.y = fmaf(x, tt.y, acc.y);
         }
-        sAi[(bi + r) * LA + bj + c] = -a0;
-        sAi[(bi + r) * LA + bj + c + 1] = -a1;
+        *reinterpret_cast<float2*>(sAi + (bi + r) * LA + bj + c) = make_float2(-acc.x, -acc.y);
     }
     __syncthreads();
     {   // T = L[32:64][0:32] A[0:32][0:32]; four outputs per thread
         const int r = tid >> 3, c = (tid & 7) * 4;
-        float t[4] = {0.f, 0.f, 0.f, 0.f};
+        float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 8
         for (int k = 0; k < 32; ++k) {
             const float l = sLt[k * BT + 32 + r];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) t[e] = fmaf(l, sAi[k * LA + c + e], t[e]);
+            const float4 a = *reinterpret_cast<const float4*>(sAi + k * LA + c);
+            t.x = fmaf(l, a.x, t.x);
+            t.y = fmaf(l, a.y, t.y);
+            t.z = fmaf(l, a.z, t.z);
+            t.w = fmaf(l, a.w, t.w);
         }
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sT[r * LT2 + c + e] = t[e];
+        *reinterpret_cast<float4*>(sT + r * LT2 + c) = t;
     }
     __syncthreads();
     {   // A[32:64][0:32] = -A[32:64][32:64] T
         const int r = tid >> 3, c = (tid & 7) * 4;
-        float a[4] = {0.f, 0.f, 0.f, 0.f};
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 8
         for (int k = 0; k < 32; ++k) {
             const float x = sAi[(32 + r) * LA + 32 + k];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) a[e] = fmaf(x, sT[k * LT2 + c + e], a[e]);
+            const float4 tt = *reinterpret_cast<const float4*>(sT + k * LT2 + c);
+            acc.x = fmaf(x, tt.x, acc.x);
+            acc.y = fmaf(x, tt.y, acc.y);
+            acc.z = fmaf(x, tt.z, acc.z);
+            acc.w = fmaf(x, tt.w, acc.w);
         }
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sAi[(32 + r) * LA + c + e] = -a[e];
+        *reinterpret_cast<float4*>(sAi + (32 + r) * LA + c) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
     }
     __syncthreads();
 }
@@ -157,8 +162,9 @@ constexpr int P_BA = 65536;        //   after MMA 1: A bf16 [64][64], K-major   
 constexpr int P_BB = 65536 + 8192; //                A diag(beta) bf16 [64][64], K-major      8 KB
 constexpr int P_AIF = 65536 + 16384;  //              A fp32 [64][LA] (the blocked inverse)  16.3 KB
 constexpr int P_TMP = 8192;        //   after MMA 1 (rows 64..127 of A1's first atom): products  4.2 KB
-constexpr int P_MISC = P_AIF + 4 * BT * LA;    // beta [64], 2^c [128], 2^(G2_last - c) [128]
-constexpr int P_BAR = P_MISC + 4 * (BT + 2 * D);
+constexpr int P_MISC = P_AIF + 4 * BT * LA;    // beta [64], 2^c [128], 2^(G2_last - c) [128],
+                                               // cumsum exchange: segment total [128], hi, lo [2][128]
+constexpr int P_BAR = P_MISC + 4 * (BT + 2 * D + 5 * D);
 constexpr size_t PREP_SMEM = P_BAR + 64 + 1024;
 static_assert(P_ALPHA + 4 * BT * LG <= P_MISC, "the G tile overlaps the constants");
 static_assert(P_TMP + 4 * 32 * LT2 <= 16384, "inverse scratch overlaps E'");
@@ -207,7 +213,7 @@ __global__ void __launch_bounds__(PT, 2)
         tc::tma_load3(sb + P_V + 8192, &tmv, 64, h, tok0, bld);
         if (GATE == 2) tc::tma_load3(sb + P_ALPHA, &tmg, 0, h, tok0, bld);
     }
-    if (tid < BT) sBeta[tid] = (tid < n) ? bfx(beta + (size_t)(tok0 + tid) * H + h) : 0.f;
+    const float beta_r = (tid < BT && tid < n) ? bfx(beta + (size_t)(tok0 + tid) * H + h) : 0.f;
     if (GATE != 2) {
         // scalar gate: the G tile repeats the token's log-decay; no gate: zeros
         for (int idx = tid; idx < BT * D / 4; idx += PT) {
@@ -227,12 +233,17 @@ __global__ void __launch_bounds__(PT, 2)
     bool ok = wait_all(bld, 0, t.err);
     if (!ok && tid == 0) tc::mbar_wait(bld, 0);   // let late tiles land before the CTA can leave
 
-    // a1: cumsum by 2 segments of 32 rows per feature (lanes 2c, 2c+1), range, midpoint anchor;
-    // alpha = 2^(G2 - c) replaces G2 (one exp2 per element; every decay factor of the chunk is
-    // alpha times a per-feature constant or its reciprocal)
+    // a1: cumsum, one feature per lane: warps 0-3 rows 0..31, warps 4-7 rows 32..63 (segment
+    // totals and ranges exchanged through shared memory), range, midpoint anchor; alpha =
+    // 2^(G2 - c) replaces G2 (one exp2 per element; every decay factor of the chunk is alpha
+    // times a per-feature constant or its reciprocal)
+    if (tid < BT) sBeta[tid] = beta_r;
     int wide_col = 0;
     if (ok) {
-        const int col = tid >> 1, seg = tid & 1;
+        float* sTot = sAL + D;       // [128] total of rows 0..31
+        float* sHi = sTot + D;       // [2][128]
+        float* sLo = sHi + 2 * D;    // [2][128]
+        const int col = tid & (D - 1), seg = tid >> 7;
         float x[32];
         float acc = 0.f;
 #pragma unroll
@@ -241,8 +252,9 @@ __global__ void __launch_bounds__(PT, 2)
             acc += (row < n) ? sA[row * LG + col] : 0.f;
             x[r] = acc;
         }
-        float pre = __shfl_up_sync(0xffffffffu, acc, 1, 2);
-        if (seg == 0) pre = 0.f;
+        if (seg == 0) sTot[col] = acc;
+        __syncthreads();
+        const float pre = seg ? sTot[col] : 0.f;
         float hi = -INFINITY, lo = INFINITY;
 #pragma unroll
         for (int r = 0; r < 32; ++r) {
@@ -252,16 +264,18 @@ __global__ void __launch_bounds__(PT, 2)
                 lo = fminf(lo, x[r]);
             }
         }
-        hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, 1));
-        lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, 1));
+        sHi[seg * D + col] = hi;
+        sLo[seg * D + col] = lo;
+        __syncthreads();
+        hi = fmaxf(sHi[col], sHi[D + col]);
+        lo = fminf(sLo[col], sLo[D + col]);
         const float cc = 0.5f * (hi + lo);
-        const float glast = __shfl_sync(0xffffffffu, x[31], lane | 1);   // G2 at row 63 = last token
 #pragma unroll
         for (int r = 0; r < 32; ++r) sA[(32 * seg + r) * LG + col] = exp2f(x[r] - cc);
-        if (seg == 0) {
+        if (seg == 1) {   // G2 at row 63 = last token
             sC2[col] = exp2f(cc);
-            sAL[col] = exp2f(glast - cc);
-            f.GL[ch * D + col] = glast;
+            sAL[col] = exp2f(x[31] - cc);
+            f.GL[ch * D + col] = x[31];
         }
         wide_col = (hi - lo) > PREP_RANGE_LOG2;
     }
