@@ -461,12 +461,21 @@ constexpr int STG_KG = 32768;                // F   [64][128]  16 KB (read MN-ma
 constexpr int STG_AQ = 49152;                // C_q [64][64]    8 KB
 constexpr int STG_BYTES = 57344;
 constexpr int OFF_OST = OFF_STAGE + 2 * STG_BYTES;   // output staging, 2 x [64][128] bf16 tile images, 32 KB
-constexpr int OFF_LAM = OFF_OST + 2 * BT * D * 2;     // lambda [128] fp32
-constexpr int OFF_TST = OFF_LAM + 512;                 // per-warp transpose staging, 8 x 1280 B
-constexpr int OFF_BAR = OFF_TST + 8 * 1280;
+// recompute mode (S and R saved, no output): the same region holds the S and R tile images of
+// two chunks, written to HBM by one bulk copy each
+constexpr int OFF_HST = OFF_OST;                       // 2 x S [128][128] bf16, 64 KB
+constexpr int OFF_RST = OFF_HST + 2 * D * D * 2;       // 2 x R [64][128] bf16, 32 KB
+// lambda [128] fp32, per-warp transpose staging (8 x 1280 B), barriers: after the staging the
+// mode uses (a smaller map leaves more of the SM's shared storage to the L1 cache)
+template <int MODE>
+struct ScanMap {
+    static constexpr int LAM = (MODE == 2) ? OFF_RST + 2 * BT * D * 2 : OFF_OST + 2 * BT * D * 2;
+    static constexpr int TST = LAM + 512;
+    static constexpr int BAR = TST + 8 * 1280;
+    static constexpr int SMEM = BAR + 64 + 1024;
+    static_assert(SMEM <= 232448, "scan shared memory above the per-block limit");
+};
 static_assert(OFF_OST % 1024 == 0, "swizzled TMA stores need 1024-byte aligned tiles");
-constexpr int SCAN_SMEM = OFF_BAR + 64 + 1024;
-static_assert(SCAN_SMEM <= 232448, "scan shared memory above the per-block limit");
 
 // TMEM columns: S^T fp32 [0,128); two buffers [D1 | O^T] of 128 columns at
 // [128,256) and [256,384), where one N = 128 pass S^T [W ; Q_g]^T gives D1 = S^T W^T
@@ -545,8 +554,8 @@ __device__ __forceinline__ void fscan_compute(const Shape& s, const float* __res
                                               int c0, int c1) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = warp & 3, half = warp >> 2;
-    float* sLam = reinterpret_cast<float*>(base + OFF_LAM);
-    bf16* tst = reinterpret_cast<bf16*>(base + OFF_TST + warp * 1280);
+    float* sLam = reinterpret_cast<float*>(base + ScanMap<MODE>::LAM);
+    bf16* tst = reinterpret_cast<bf16*>(base + ScanMap<MODE>::TST + warp * 1280);
     const int H = s.H;
     const int vcol = 32 * quad + lane;  // TMEM lane and value column of this thread
     const uint32_t tl = tc::taddr(tb, 32 * quad, 0);
@@ -640,7 +649,25 @@ __device__ __forceinline__ void fscan_compute(const Shape& s, const float* __res
         tc::named_sync(NB_AR, ST_ALL);
         // 4. while the state update runs: the saved S and R, the output of chunk c-1 (one output
         //    barrier per TMEM buffer, so the commit of this chunk's output cannot be taken for it)
-        if (MODE & 2) {
+        if (MODE == 2) {
+            // S (from the bf16 S^T operand still in TMEM) and R as tile images into staging
+            // buffer it&1; the issuer copies them to HBM after the next hand-over
+            bf16* hs = reinterpret_cast<bf16*>(base + OFF_HST) + (it & 1) * D * D;
+            bf16* rs = reinterpret_cast<bf16*>(base + OFF_RST) + (it & 1) * BT * D;
+#pragma unroll
+            for (int hq = 0; hq < 2; ++hq) {
+                float pv[16];
+                tc::tmem_ld16(tl + T_AS + kb / 2 + 16 * hq, pv);
+                tc::tmem_wait_ld();
+                const uint16_t* p16 = reinterpret_cast<const uint16_t*>(pv);
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    reinterpret_cast<uint16_t*>(hs)[tile_el(D, kb + 32 * hq + j, vcol)] = p16[j];
+            }
+#pragma unroll
+            for (int j = 0; j < 32; ++j) rs[tile_el(BT, ib + j, vcol)] = __float2bfloat16_rn(rv[j >> 4][j & 15]);
+            tc::fence_async_smem();
+        } else if (MODE & 2) {
             // the bf16 S^T of this chunk is still in its TMEM operand buffer
 #pragma unroll
             for (int hq = 0; hq < 2; ++hq) {
@@ -735,13 +762,20 @@ __device__ __forceinline__ void fscan_issue(const Shape& s, const Table& t, cons
         }
         // the output of chunk c-2 (a full chunk), staged by the compute warps during chunk c-1
         if ((MODE & 1) && it >= 2 && pl == BT) fscan_tma_out(tmo, sb + OFF_OST + (it & 1) * BT * D * 2, pt, h, lane);
+        // recompute mode: S and R of chunk c-1, staged during chunk c-1
+        if (MODE == 2 && it >= 1 && lane == 0) {
+            const size_t cp = (size_t)(c - 1) * H + h;
+            tc::bulk_s2g(f.HS + cp * D * D, sb + OFF_HST + ((it - 1) & 1) * D * D * 2, D * D * 2);
+            tc::bulk_s2g(f.R + cp * BT * D, sb + OFF_RST + ((it - 1) & 1) * BT * D * 2, BT * D * 2);
+            tc::bulk_commit();
+        }
         if ((MODE & 1) && it >= 1) {   // extent of chunk c-1, whose output is stored next iteration
             pl = __ldg(t.chunk_len + c - 1);
             pt = __ldg(t.chunk_tok0 + c - 1);
         }
         // the staging tile stored during chunk c-1 is rewritten after this hand-over; the one
         // stored just now may still be read (it is rewritten during chunk c+1)
-        if ((MODE & 1) && lane == 0) tc::bulk_wait_read_prev();
+        if (lane == 0) tc::bulk_wait_read_prev();
         __syncwarp();
         tc::named_sync(NB_AR, ST_ALL);
         tc::fence_after_sync();
@@ -768,7 +802,7 @@ __global__ void __launch_bounds__(ST_ALL, 1)
     extern __shared__ unsigned char smem_raw[];
     unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                            ~static_cast<uintptr_t>(1023));
-    uint64_t* bar = reinterpret_cast<uint64_t*>(base + OFF_BAR);   // D1, state update, output (x2)
+    uint64_t* bar = reinterpret_cast<uint64_t*>(base + ScanMap<MODE>::BAR);   // D1, state update, output (x2)
     uint64_t* full = bar + 4;                                        // operand stages 0, 1
     uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 6);
     const uint32_t sb = tc::smem_u32(base);
@@ -803,6 +837,15 @@ __global__ void __launch_bounds__(ST_ALL, 1)
         for (; waited < filled; ++waited) tc::mbar_wait(&full[waited & 1], (waited >> 1) & 1);
     tc::fence_before_sync();
     __syncthreads();
+    // recompute mode: S and R of the last chunk (staged after the issuer's loop ended)
+    if (MODE == 2 && issuer && c1 > c0 && (tid & 31) == 0) {
+        const int last = c1 - 1 - c0;
+        const size_t cp = (size_t)(c1 - 1) * s.H + h;
+        tc::bulk_s2g(f.HS + cp * D * D, sb + OFF_HST + (last & 1) * D * D * 2, D * D * 2);
+        tc::bulk_s2g(f.R + cp * BT * D, sb + OFF_RST + (last & 1) * BT * D * 2, BT * D * 2);
+        tc::bulk_commit();
+        tc::bulk_wait_all();
+    }
     // the last two outputs (staged after the issuer's loop ended)
     if ((MODE & 1) && issuer && c1 > c0) {
         const int last = c1 - 1 - c0, lane = tid & 31;
@@ -831,13 +874,13 @@ cudaError_t run_prep(const Shape& s, const void* q, const void* k, const void* v
 
 template <int MODE>
 cudaError_t run_scan(const Shape& s, const float* h0, Table t, FwdTC f, void* o, float* ht, cudaStream_t st) {
-    cudaError_t e = set_smem_once<k_fwd_scan_tc<MODE>>(SCAN_SMEM);
+    cudaError_t e = set_smem_once<k_fwd_scan_tc<MODE>>(ScanMap<MODE>::SMEM);
     if (e != cudaSuccess) return e;
     CUtensorMap mo;
     memset(&mo, 0, sizeof(mo));
     if ((MODE & 1) && !tmap_rows_bf16(&mo, o, s.Ttot, s.H, D)) return cudaErrorInvalidValue;
     dim3 grid(s.N, s.H);
-    k_fwd_scan_tc<MODE><<<grid, ST_ALL, SCAN_SMEM, st>>>(s, mo, h0, t, f, (bf16*)o, ht);
+    k_fwd_scan_tc<MODE><<<grid, ST_ALL, ScanMap<MODE>::SMEM, st>>>(s, mo, h0, t, f, (bf16*)o, ht);
     return cudaGetLastError();
 }
 
