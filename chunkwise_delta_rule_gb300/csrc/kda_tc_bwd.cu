@@ -385,12 +385,14 @@ __global__ void __launch_bounds__(CT, 1)
 
     const int c = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = warp & 3, grp = warp >> 2;
-    const int n = t.chunk_len[c];
-    if (n <= 0) return;
+    // the chunk's extent and flag, read together (one latency)
     const int H = s.H;
     const size_t ch = (size_t)c * H + h;
-    if (GATE != 0 && f.WIDE[ch]) return;  // wide gate range: fp32 CUDA-core consumers
+    const int n = t.chunk_len[c];
     const int tok0 = t.chunk_tok0[c];
+    const int wide = (GATE != 0) ? f.WIDE[ch] : 0;
+    if (n <= 0) return;
+    if (wide) return;  // wide gate range: fp32 CUDA-core consumers
     const float scale = s.scale;
 
     // beta (read now, stored to shared memory once the loads below are in flight)
@@ -734,8 +736,10 @@ __global__ void __launch_bounds__(CT, 1)
             }
             __syncthreads();
             if (GATE == 2) {
-                // reverse in-chunk cumsum by 4 segments of 16 rows per feature
-                const int col = tid >> 2, seg = tid & 3;
+                // reverse in-chunk cumsum, one feature per lane and 4 segments of 16 rows (warps
+                // 4s..4s+3); segment totals through shared memory (the endpoint partials are
+                // consumed), so each row of dg is written by one warp as 512 contiguous bytes
+                const int col = tid & (D - 1), seg = tid >> 7;
                 float x[16];
                 float acc = 0.f;
 #pragma unroll
@@ -744,11 +748,11 @@ __global__ void __launch_bounds__(CT, 1)
                     acc += (row < n) ? sGQ[row * LG + col] + sGE[row * LG + col] : 0.f;
                     x[r] = acc;
                 }
-                float nxt = __shfl_down_sync(0xffffffffu, acc, 1, 4);
-                if (seg > 2) nxt = 0.f;
-                float t2 = __shfl_down_sync(0xffffffffu, acc + nxt, 2, 4);
-                if (seg > 1) t2 = 0.f;
-                const float off = nxt + t2;  // sum of the later segments
+                float* sSeg = sEndP;   // [4][128]
+                sSeg[seg * D + col] = acc;
+                __syncthreads();
+                float off = 0.f;   // sum of the later segments
+                for (int s2 = seg + 1; s2 < 4; ++s2) off += sSeg[s2 * D + col];
 #pragma unroll
                 for (int r = 0; r < 16; ++r) {
                     const int row = 16 * seg + r;
