@@ -30,13 +30,13 @@ constexpr int SL = 32;  // value columns of S per slice in k_bwd_dstate
 
 // IT: element type of the P, R, S and S+bar inputs: fp32 row-major here, bf16
 // tile images (tile_el) when finishing the wide chunks of the tensor-core
-// path, selected by `only`.
+// path, listed in `list`.
 template <typename TI, typename IT, int D>
-__global__ void __launch_bounds__(NTHREADS, 1)
-    k_bwd_dstate(Shape s, const TI* __restrict__ dout, const TI* __restrict__ v,
-                 const TI* __restrict__ beta, Table t, const IT* __restrict__ Pin,
-                 const IT* __restrict__ Rin, const IT* __restrict__ Sin, const IT* __restrict__ SBin,
-                 const int32_t* __restrict__ only, Bwd b, TI* __restrict__ dv) {
+__device__ __forceinline__ void dstate_chunk(int c, int h, const Shape& s, const TI* __restrict__ dout,
+                                             const TI* __restrict__ v, const TI* __restrict__ beta, const Table& t,
+                                             const IT* __restrict__ Pin, const IT* __restrict__ Rin,
+                                             const IT* __restrict__ Sin, const IT* __restrict__ SBin, const Bwd& b,
+                                             TI* __restrict__ dv) {
     constexpr int LD = D + 1, LS = SL + 1;
     extern __shared__ float smem[];
     float* sO = smem;              // [BT][LD] dO
@@ -45,13 +45,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     float* sS = sR + BT * LD;      // [D][LS] slice of S
     float* sT = sS + D * LS;       // [D][LS] slice of S+bar
 
-    const int c = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+    const int tid = threadIdx.x;
     const int len = t.chunk_len[c];
     if (len <= 0) return;
     const int tok0 = t.chunk_tok0[c];
     const int H = s.H;
     const size_t ch = (size_t)c * H + h;
-    if (only && !only[ch]) return;
     const int lane = tid & 31, warp = tid >> 5;
 
     constexpr bool IMG = sizeof(IT) == 2;
@@ -149,11 +148,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 }
 
 template <typename TI, int D, int GATE>
-__global__ void __launch_bounds__(NTHREADS, 1)
-    k_bwd_intra(Shape s, const TI* __restrict__ q, const TI* __restrict__ k,
-                const TI* __restrict__ beta, const float* __restrict__ g, Table t,
-                const int32_t* __restrict__ only, Bwd b, TI* __restrict__ dq, TI* __restrict__ dk,
-                TI* __restrict__ dbeta, float* __restrict__ dg) {
+__device__ __forceinline__ void intra_chunk(int c, int h, const Shape& s, const TI* __restrict__ q,
+                                            const TI* __restrict__ k, const TI* __restrict__ beta,
+                                            const float* __restrict__ g, const Table& t, const Bwd& b,
+                                            TI* __restrict__ dq, TI* __restrict__ dk, TI* __restrict__ dbeta,
+                                            float* __restrict__ dg) {
     constexpr int LD = D + 1, LA = BT + 1;
     extern __shared__ float smem[];
     float* sK = smem;               // [BT][LD] keys
@@ -167,7 +166,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     float* sC = sBeta + BT;         // [D] center of each feature
     float* sRow = sC + D;           // [BT] per-row reductions
 
-    const int c = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+    const int tid = threadIdx.x;
     const int len = t.chunk_len[c];
     if (len <= 0) return;
     const int tok0 = t.chunk_tok0[c];
@@ -175,7 +174,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const size_t ch = (size_t)c * H + h;
     const float scale = s.scale;
     const int lane = tid & 31, warp = tid >> 5;
-    if (only && !only[ch]) return;
 
     for (int idx = tid; idx < BT * D; idx += NTHREADS) {
         const int r = idx / D, col = idx % D;
@@ -466,44 +464,82 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
 }
 
+// With a list (count, then chunk slot * H + head): only the listed chunks,
+// spread over a grid of one CTA per SM; without: one CTA per (chunk slot, head).
+template <typename TI, typename IT, int D>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    k_bwd_dstate(Shape s, const TI* __restrict__ dout, const TI* __restrict__ v,
+                 const TI* __restrict__ beta, Table t, const IT* __restrict__ Pin,
+                 const IT* __restrict__ Rin, const IT* __restrict__ Sin, const IT* __restrict__ SBin,
+                 const int32_t* __restrict__ list, Bwd b, TI* __restrict__ dv) {
+    if (list) {
+        const int cnt = list[0];
+        for (int w = blockIdx.x; w < cnt; w += gridDim.x) {
+            const int ch = list[1 + w];
+            dstate_chunk<TI, IT, D>(ch / s.H, ch % s.H, s, dout, v, beta, t, Pin, Rin, Sin, SBin, b, dv);
+            __syncthreads();
+        }
+    } else {
+        dstate_chunk<TI, IT, D>(blockIdx.x, blockIdx.y, s, dout, v, beta, t, Pin, Rin, Sin, SBin, b, dv);
+    }
+}
+
+template <typename TI, int D, int GATE>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    k_bwd_intra(Shape s, const TI* __restrict__ q, const TI* __restrict__ k,
+                const TI* __restrict__ beta, const float* __restrict__ g, Table t,
+                const int32_t* __restrict__ list, Bwd b, TI* __restrict__ dq, TI* __restrict__ dk,
+                TI* __restrict__ dbeta, float* __restrict__ dg) {
+    if (list) {
+        const int cnt = list[0];
+        for (int w = blockIdx.x; w < cnt; w += gridDim.x) {
+            const int ch = list[1 + w];
+            intra_chunk<TI, D, GATE>(ch / s.H, ch % s.H, s, q, k, beta, g, t, b, dq, dk, dbeta, dg);
+            __syncthreads();
+        }
+    } else {
+        intra_chunk<TI, D, GATE>(blockIdx.x, blockIdx.y, s, q, k, beta, g, t, b, dq, dk, dbeta, dg);
+    }
+}
+
 template <typename TI, typename IT, int D>
 cudaError_t run_dstate(const Shape& s, const void* dout, const void* v, const void* beta, Table t,
-                       const IT* P, const IT* R, const IT* S, const IT* SB, const int32_t* only, Bwd b,
+                       const IT* P, const IT* R, const IT* S, const IT* SB, const int32_t* list, Bwd b,
                        void* dv, cudaStream_t st) {
     constexpr int LD = D + 1, LS = SL + 1;
     constexpr size_t smem = sizeof(float) * (3 * BT * LD + 2 * D * LS);
     auto kern = k_bwd_dstate<TI, IT, D>;
     cudaError_t e = set_smem_once<k_bwd_dstate<TI, IT, D>>(smem);
     if (e != cudaSuccess) return e;
-    dim3 grid(s.NC, s.H);
+    const dim3 grid = list ? dim3(sm_count()) : dim3(s.NC, s.H);
     kern<<<grid, NTHREADS, smem, st>>>(s, (const TI*)dout, (const TI*)v, (const TI*)beta, t, P, R, S, SB,
-                                       only, b, (TI*)dv);
+                                       list, b, (TI*)dv);
     return cudaGetLastError();
 }
 
 template <typename TI, int D, int GATE>
 cudaError_t run_intra(const Shape& s, const void* q, const void* k, const void* beta, const float* g,
-                      Table t, const int32_t* only, Bwd b, void* dq, void* dk, void* dbeta, float* dg,
+                      Table t, const int32_t* list, Bwd b, void* dq, void* dk, void* dbeta, float* dg,
                       cudaStream_t st) {
     constexpr int LD = D + 1, LA = BT + 1;
     constexpr size_t smem = sizeof(float) * (5 * BT * LD + 2 * BT * LA + 2 * BT + D);
     auto kern = k_bwd_intra<TI, D, GATE>;
     cudaError_t e = set_smem_once<k_bwd_intra<TI, D, GATE>>(smem);
     if (e != cudaSuccess) return e;
-    dim3 grid(s.NC, s.H);
-    kern<<<grid, NTHREADS, smem, st>>>(s, (const TI*)q, (const TI*)k, (const TI*)beta, g, t, only, b,
+    const dim3 grid = list ? dim3(sm_count()) : dim3(s.NC, s.H);
+    kern<<<grid, NTHREADS, smem, st>>>(s, (const TI*)q, (const TI*)k, (const TI*)beta, g, t, list, b,
                                        (TI*)dq, (TI*)dk, (TI*)dbeta, dg);
     return cudaGetLastError();
 }
 
 template <typename TI, int D>
 cudaError_t run_intra_gate(int gate, const Shape& s, const void* q, const void* k, const void* beta,
-                           const float* g, Table t, const int32_t* only, Bwd b, void* dq, void* dk,
+                           const float* g, Table t, const int32_t* list, Bwd b, void* dq, void* dk,
                            void* dbeta, float* dg, cudaStream_t st) {
     switch (gate) {
-        case 0: return run_intra<TI, D, 0>(s, q, k, beta, g, t, only, b, dq, dk, dbeta, dg, st);
-        case 1: return run_intra<TI, D, 1>(s, q, k, beta, g, t, only, b, dq, dk, dbeta, dg, st);
-        default: return run_intra<TI, D, 2>(s, q, k, beta, g, t, only, b, dq, dk, dbeta, dg, st);
+        case 0: return run_intra<TI, D, 0>(s, q, k, beta, g, t, list, b, dq, dk, dbeta, dg, st);
+        case 1: return run_intra<TI, D, 1>(s, q, k, beta, g, t, list, b, dq, dk, dbeta, dg, st);
+        default: return run_intra<TI, D, 2>(s, q, k, beta, g, t, list, b, dq, dk, dbeta, dg, st);
     }
 }
 
@@ -534,9 +570,9 @@ cudaError_t launch_bwd_wide(const Shape& s, int gate, const void* q, const void*
                             BwdTC bt, Bwd scratch, void* dq, void* dk, void* dv, void* dbeta, float* dg,
                             cudaStream_t st) {
     cudaError_t e = run_dstate<__nv_bfloat16, __nv_bfloat16, 128>(s, dout, v, beta, t, bt.P, f.R, f.HS, bt.SBP,
-                                                                  f.WIDE, scratch, dv, st);
+                                                                  f.WLIST, scratch, dv, st);
     if (e != cudaSuccess) return e;
-    return run_intra_gate<__nv_bfloat16, 128>(gate, s, q, k, beta, g, t, f.WIDE, scratch, dq, dk, dbeta, dg, st);
+    return run_intra_gate<__nv_bfloat16, 128>(gate, s, q, k, beta, g, t, f.WLIST, scratch, dq, dk, dbeta, dg, st);
 }
 
 }  // namespace kda

@@ -82,6 +82,7 @@ struct FwdTC {
     float* U;             // [NC,H,BT,D]  U = A Z
     float* GL;            // [NC,H,D]     cumulative log2-decay at the last token
     int32_t* WIDE;        // [NC,H]       1: gate range too wide for one anchor
+    int32_t* WLIST;       // [1 + NC*H]   count, then chunk slot * H + head of every WIDE chunk
     // backward-only (null in the forward)
     __nv_bfloat16* AI;    // [NC,H,BT,BT] A = (I + L)^-1
     __nv_bfloat16* HS;    // [NC,H,D,D]   state entering the chunk, [key][value]
@@ -157,6 +158,18 @@ __device__ __forceinline__ void zero(float (&acc)[TM][TN]) {
 
 // Raises a kernel's dynamic shared-memory limit once per device (so that no
 // attribute call is issued again once a stream is being captured).
+// Streaming multiprocessors of the current device (cached per device).
+inline int sm_count() {
+    static int cnt[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (!cnt[dev]) {
+        int v = 0;
+        cnt[dev] = (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) ? v : 148;
+    }
+    return cnt[dev];
+}
+
 template <auto Kern>
 inline cudaError_t set_smem_once(size_t bytes) {
     static int done[64] = {0};

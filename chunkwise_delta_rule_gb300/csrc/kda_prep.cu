@@ -20,9 +20,10 @@ namespace {
 // TCOUT: prepare only the chunks the tensor-core prep flagged as too wide for
 // one anchor, and write the tensor-core path's layouts (bf16 tile images).
 template <typename TI, int D, int GATE, bool TCOUT>
-__global__ void __launch_bounds__(NTHREADS, 1)
-    k_prep(Shape s, const TI* __restrict__ q, const TI* __restrict__ k, const TI* __restrict__ v,
-           const TI* __restrict__ beta, const float* __restrict__ g, Table t, Fwd f, FwdTC ft) {
+__device__ __forceinline__ void prep_chunk(int c, int h, const Shape& s, const TI* __restrict__ q,
+                                           const TI* __restrict__ k, const TI* __restrict__ v,
+                                           const TI* __restrict__ beta, const float* __restrict__ g,
+                                           const Table& t, const Fwd& f, const FwdTC& ft) {
     constexpr int LD = D + 1;       // padded row stride of [BT x D] tiles
     constexpr int LA = BT + 1;      // padded row stride of [BT x BT] tiles
     extern __shared__ float smem[];
@@ -35,13 +36,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     float* sAi = sAkk + BT * LA;    // [BT][LA]
     float* sBeta = sAi + BT * LA;   // [BT]
 
-    const int c = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+    const int tid = threadIdx.x;
     const int n = t.chunk_len[c];
     if (n <= 0) return;
     const int tok0 = t.chunk_tok0[c];
     const int H = s.H;
     const size_t ch = (size_t)c * H + h;
-    if (TCOUT && ft.WIDE[ch] == 0) return;
 
     // ---- load chunk rows (rows >= n are zero keys/queries and zero decay)
     for (int idx = tid; idx < BT * D; idx += NTHREADS) {
@@ -201,6 +201,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
 }
 
+// TCOUT: the chunks the tensor-core prep listed as wide, spread over a grid of
+// one CTA per SM; otherwise one CTA per (chunk slot, head).
+template <typename TI, int D, int GATE, bool TCOUT>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    k_prep(Shape s, const TI* __restrict__ q, const TI* __restrict__ k, const TI* __restrict__ v,
+           const TI* __restrict__ beta, const float* __restrict__ g, Table t, Fwd f, FwdTC ft) {
+    if (TCOUT) {
+        const int cnt = ft.WLIST[0];
+        for (int w = blockIdx.x; w < cnt; w += gridDim.x) {
+            const int ch = ft.WLIST[1 + w];
+            prep_chunk<TI, D, GATE, TCOUT>(ch / s.H, ch % s.H, s, q, k, v, beta, g, t, f, ft);
+            __syncthreads();
+        }
+    } else {
+        prep_chunk<TI, D, GATE, TCOUT>(blockIdx.x, blockIdx.y, s, q, k, v, beta, g, t, f, ft);
+    }
+}
+
 template <typename TI, int D, int GATE, bool TCOUT>
 cudaError_t run(const Shape& s, const void* q, const void* k, const void* v, const void* beta,
                 const float* g, Table t, Fwd f, FwdTC ft, cudaStream_t st) {
@@ -209,7 +227,7 @@ cudaError_t run(const Shape& s, const void* q, const void* k, const void* v, con
     auto kern = k_prep<TI, D, GATE, TCOUT>;
     cudaError_t e = set_smem_once<k_prep<TI, D, GATE, TCOUT>>(smem);
     if (e != cudaSuccess) return e;
-    dim3 grid(s.NC, s.H);
+    const dim3 grid = TCOUT ? dim3(sm_count()) : dim3(s.NC, s.H);
     kern<<<grid, NTHREADS, smem, st>>>(s, (const TI*)q, (const TI*)k, (const TI*)v, (const TI*)beta, g, t, f, ft);
     return cudaGetLastError();
 }

@@ -280,7 +280,10 @@ __global__ void __launch_bounds__(PT, 2)
         wide_col = (hi - lo) > PREP_RANGE_LOG2;
     }
     const bool wide = __syncthreads_or(wide_col) != 0;
-    if (tid == 0 && ok) f.WIDE[ch] = wide ? 1 : 0;
+    if (tid == 0 && ok) {
+        f.WIDE[ch] = wide ? 1 : 0;
+        if (wide) f.WLIST[1 + atomicAdd(f.WLIST, 1)] = (int32_t)ch;   // for the CUDA-core kernels
+    }
     if (!wide && ok) {
         // a2 operands (bf16), in place over the loaded tiles, one pass over the row chunks of this
         // thread: A1 rows 0..63 beta_i k_i alpha_i, rows 64..127 s q_i alpha_i; B1 rows j:
@@ -861,6 +864,8 @@ template <int GATE, bool BWD>
 cudaError_t run_prep(const Shape& s, const void* q, const void* k, const void* v, const void* beta,
                      const float* g, Table t, FwdTC f, cudaStream_t st) {
     cudaError_t e = set_smem_once<k_prep_tc<GATE, BWD>>(PREP_SMEM);
+    if (e != cudaSuccess) return e;
+    e = cudaMemsetAsync(f.WLIST, 0, sizeof(int32_t), st);   // the list of wide chunks starts empty
     if (e != cudaSuccess) return e;
     CUtensorMap mq, mk, mv, mg;
     memset(&mg, 0, sizeof(mg));
