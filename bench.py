@@ -1,12 +1,14 @@
 #!/usr/bin/env python
 """Benchmark of the chunkwise gated delta rule on one GB300 (or N replicas).
 
-One step = the forward pass and the complete backward pass (recompute policy)
-of the KDA workload B=2, T=8192, H=32, dk=dv=128, bf16 I/O, per-channel gate
+One step = the forward pass and the complete backward pass of the KDA workload B=2, T=8192, H=32, dk=dv=128, bf16 I/O, per-channel gate
 (the configuration the tokens/s headline is quoted on), synthetic seeded
-inputs resident in HBM. Prints one JSON line.
+inputs resident in HBM. Prints one JSON line. The policy decides what the
+backward starts from: "save" (the forward keeps its chunk intermediates in a
+saved buffer) or "recompute" (the backward rebuilds them from the inputs).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--policy save|recompute]
 
 Under torchrun every rank runs its own replica (weak scaling, no data-path
 collective); the elapsed time is the max over ranks.
@@ -256,15 +258,18 @@ def run_ours(args):
         case_cpu = heads_subset(case_cpu, args.heads)
     case = case_cpu.to(dev)
     lib = _lib.load()
+    save = 1 if args.policy == "save" else 0
     p = kda.make_problem(case.q, case.k, case.v, case.g, case.beta, gate=case.gate,
-                         scale=case.scale, initial_state=case.h0, cu_seqlens=case.cu_seqlens)
+                         scale=case.scale, initial_state=case.h0, cu_seqlens=case.cu_seqlens,
+                         save_policy=save)
     wf = torch.empty(kda.kda_workspace_size(p, False), dtype=torch.uint8, device=dev)
     wb = torch.empty(kda.kda_workspace_size(p, True), dtype=torch.uint8, device=dev)
+    sv = torch.empty(kda.kda_saved_size(p), dtype=torch.uint8, device=dev) if save else None
     l2 = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
     def step():
-        kda.kda_chunk_fwd(p, workspace=wf)
-        kda.kda_chunk_bwd(p, case.do, case.dht, workspace=wb)
+        kda.kda_chunk_fwd(p, workspace=wf, saved=sv)
+        kda.kda_chunk_bwd(p, case.do, case.dht, workspace=wb, saved=sv)
 
     for _ in range(args.warmup):
         step()
@@ -296,9 +301,9 @@ def run_ours(args):
     for i in range(K):
         l2.zero_()                                  # flush L2 between timed steps
         ev[i][0].record()
-        kda.kda_chunk_fwd(p, workspace=wf)
+        kda.kda_chunk_fwd(p, workspace=wf, saved=sv)
         ev[i][1].record()
-        kda.kda_chunk_bwd(p, case.do, case.dht, workspace=wb)
+        kda.kda_chunk_bwd(p, case.do, case.dht, workspace=wb, saved=sv)
         ev[i][2].record()
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall
@@ -379,7 +384,7 @@ def run_ours(args):
             "data": "synthetic (seeded; shapes and distributions of the workload)",
             "config": {"workload": cfg["name"] + (f"_first{case.H}heads" if args.heads else ""), "B": case.B, "T": case.T, "H": case.H, "dk": case.K,
                        "dv": case.V, "gate": case.gate, "io": cfg["io"], "chunk": BT,
-                       "policy": "recompute", "parallelism": f"replicas x{ws}",
+                       "policy": args.policy, "parallelism": f"replicas x{ws}",
                        "l2": "flushed by a 256 MiB write before every timed step"},
             "tflops": round(tflops, 2), "tflops_executed": round(tflops_exec, 2),
             "frac_bf16_peak": round(tflops / pk["bf16"], 4),
@@ -404,6 +409,8 @@ def run_e2e(args, case_cpu, dev, kda, K):
     import torch
     names = ["q", "k", "v", "g", "beta", "h0", "do", "dht"]
     host = {n: getattr(case_cpu, n).pin_memory() for n in names if getattr(case_cpu, n) is not None}
+    if case_cpu.cu_seqlens is not None:
+        host["cu_seqlens"] = case_cpu.cu_seqlens.pin_memory()
     devt = {n: torch.empty_like(t, device=dev) for n, t in host.items()}
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     outs_host = None
@@ -416,9 +423,10 @@ def run_e2e(args, case_cpu, dev, kda, K):
         for n, t in host.items():
             devt[n].copy_(t, non_blocking=True)
         p = kda.make_problem(devt["q"], devt["k"], devt["v"], devt.get("g"), devt["beta"],
-                             gate=case_cpu.gate, scale=case_cpu.scale, initial_state=devt.get("h0"))
-        o, ht, _ = kda.kda_chunk_fwd(p)
-        grads = kda.kda_chunk_bwd(p, devt["do"], devt.get("dht"))
+                             gate=case_cpu.gate, scale=case_cpu.scale, initial_state=devt.get("h0"),
+                             cu_seqlens=devt.get("cu_seqlens"), save_policy=1 if args.policy == "save" else 0)
+        o, ht, sv = kda.kda_chunk_fwd(p)
+        grads = kda.kda_chunk_bwd(p, devt["do"], devt.get("dht"), saved=sv)
         res = [o, ht] + [x for x in grads if x is not None]
         if outs_host is None:
             outs_host = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in res]
@@ -466,7 +474,9 @@ def time_oracle(case_cpu, pairs, cores):
 
 
 def cpu_baseline(case_cpu):
-    pairs, cores = oracle_sample(case_cpu)
+    # up to four (sequence, head) pairs per host core: the whole kda_bf16 workload
+    # (64 pairs) on 16 cores, some tens of core-seconds
+    pairs, cores = oracle_sample(case_cpu, pairs_wanted=min(case_cpu.N * case_cpu.H, 4 * (os.cpu_count() or 1)))
     v, dt, th = time_oracle(case_cpu, pairs, cores)
     return {"value": round(v, 2), "unit": "tokens/s", "cores": cores, "kind": "oracle",
             "sample": f"{len(pairs)} whole (sequence, head) pairs = {th} token-heads, fp64 "
@@ -516,6 +526,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--heads", type=int, default=0, help="restrict the workload to its first H heads (profiling)")
+    ap.add_argument("--policy", choices=["save", "recompute"], default="recompute",
+                    help="save: the forward keeps its intermediates for the backward; recompute: the backward rebuilds them")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
