@@ -4,8 +4,9 @@
 One step = the forward pass and the complete backward pass of the KDA workload B=2, T=8192, H=32, dk=dv=128, bf16 I/O, per-channel gate
 (the configuration the tokens/s headline is quoted on), synthetic seeded
 inputs resident in HBM. Prints one JSON line. The policy decides what the
-backward starts from: "save" (the forward keeps its chunk intermediates in a
-saved buffer) or "recompute" (the backward rebuilds them from the inputs).
+backward starts from: "save" (the default: the forward keeps its chunk
+intermediates in a saved buffer, about 1.2 GB at this workload) or
+"recompute" (the backward rebuilds them from the inputs, no saved buffer).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--policy save|recompute]
@@ -85,7 +86,7 @@ def kernel_work(case):
     gb = {"channel": 4 * d, "scalar": 4, "none": 0}[case.gate]   # log-decay bytes per token
     fl = dict(k_prep=0.0, k_fwd_scan=0.0, k_fwd_scan_recompute=0.0, k_bwd_scan=0.0,
               k_bwd_dstate=0.0, k_bwd_intra=0.0, k_prep_tc=0.0, k_fwd_scan_tc=0.0,
-              k_fwd_scan_tc_recompute=0.0, k_bwd_scan_tc=0.0, k_bwd_consumer_tc=0.0)
+              k_fwd_scan_tc_recompute=0.0, k_fwd_scan_tc_save=0.0, k_bwd_scan_tc=0.0, k_bwd_consumer_tc=0.0)
     by = dict.fromkeys(fl, 0.0)
     for n in chunk_lengths(case):
         fl["k_prep"] += 8 * n * n * d + 2 * n ** 3 / 3
@@ -97,12 +98,14 @@ def kernel_work(case):
         fl["k_prep_tc"] += 8 * n * n * d + 2 * n ** 3 / 3
         fl["k_fwd_scan_tc"] += 6 * n * d * d + 2 * n * n * d
         fl["k_fwd_scan_tc_recompute"] += 4 * n * d * d
+        fl["k_fwd_scan_tc_save"] += 4 * n * d * d
         fl["k_bwd_scan_tc"] += 6 * n * d * d + 4 * n * n * d
         fl["k_bwd_consumer_tc"] += 12 * n * n * d + 6 * n * d * d
         # tensor-core path: bf16 tiles W, F, Q_g, C_q, A, S, S+bar, R, P; fp32 U and G at the chunk end
         by["k_prep_tc"] += 3 * n * d * e + n * gb + n * e + 3 * n * d * 2 + n * n * 2 + n * d * 4 + d * 4
         by["k_fwd_scan_tc"] += 3 * n * d * 2 + n * n * 2 + n * d * 4 + d * 4 + n * d * e
         by["k_fwd_scan_tc_recompute"] += 2 * n * d * 2 + n * d * 4 + d * 4 + d * d * 2 + n * d * 2
+        by["k_fwd_scan_tc_save"] += 2 * n * d * 2 + n * d * 4 + d * 4 + d * d * 2 + n * d * 2
         by["k_bwd_scan_tc"] += 3 * n * d * 2 + 2 * n * n * 2 + d * 4 + n * d * e + d * d * 2 + n * d * 2
         by["k_bwd_consumer_tc"] += (3 * n * d * 2 + 2 * d * d * 2 + 3 * n * d * e + n * gb + n * e
                                     + 3 * n * d * e + n * e + n * gb)
@@ -323,7 +326,7 @@ def run_ours(args):
     fl_f, fl_b, fl_r = flops_model(case)
     value = ws * tokens / (step_ms * 1e-3)
     tflops = ws * (fl_f + fl_b) / (step_ms * 1e-3) / 1e12
-    tflops_exec = ws * (fl_f + fl_b + fl_r) / (step_ms * 1e-3) / 1e12
+    tflops_exec = ws * (fl_f + fl_b + (fl_r if args.policy == "recompute" else 0.0)) / (step_ms * 1e-3) / 1e12
     pk = peaks()
     launches = sum(v[0] for v in kern.values())
     # dominant kernel and its roofline
@@ -335,7 +338,7 @@ def run_ours(args):
         avg_ms = tot / n_l
         fl, by = work.get(dom, (0.0, 0.0))
         sm_mhz = clk["sm_mhz"] if clk else pk["sm_max"]
-        if dom.endswith("_tc") or dom.endswith("_tc_recompute"):
+        if "_tc" in dom:
             # which roofline binds: compare the kernel's time at either peak
             t_hbm = by / (pk["hbm"] * 1e9)
             t_tc = fl / (pk["bf16"] * 1e12)
@@ -526,7 +529,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--heads", type=int, default=0, help="restrict the workload to its first H heads (profiling)")
-    ap.add_argument("--policy", choices=["save", "recompute"], default="recompute",
+    ap.add_argument("--policy", choices=["save", "recompute"], default="save",
                     help="save: the forward keeps its intermediates for the backward; recompute: the backward rebuilds them")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":

@@ -237,6 +237,51 @@ cudaError_t traced(const char* name, cudaStream_t cs, F&& launch) {
     return e;
 }
 
+// A second stream for kernels that can run beside the caller's stream: two
+// scans of one (sequence, head) each occupy a whole SM, so when the pairs fill
+// at most half the GPU, two independent scans side by side cost one. One side
+// stream and its fork/join events per host thread and device (so threads that
+// call concurrently never share an event); created on first use and kept.
+struct Side {
+    cudaStream_t st = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+    bool tried = false;
+};
+thread_local Side t_side[64];
+
+// The side stream of the current device, or nullptr (then everything stays on
+// the caller's stream).
+Side* side_stream() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    Side& sd = t_side[dev];
+    if (!sd.tried) {
+        sd.tried = true;
+        if (cudaStreamCreateWithFlags(&sd.st, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming) != cudaSuccess) {
+            cudaGetLastError();
+            sd.st = nullptr;
+        }
+    }
+    return sd.st ? &sd : nullptr;
+}
+
+// Work enqueued on `side` after fork() follows everything already on `main`;
+// work enqueued on `main` after join() follows everything enqueued on `side`.
+cudaError_t side_fork(Side* sd, cudaStream_t main) {
+    cudaError_t e = cudaEventRecord(sd->fork, main);
+    return e != cudaSuccess ? e : cudaStreamWaitEvent(sd->st, sd->fork, 0);
+}
+cudaError_t side_join(Side* sd, cudaStream_t main) {
+    cudaError_t e = cudaEventRecord(sd->join, sd->st);
+    return e != cudaSuccess ? e : cudaStreamWaitEvent(main, sd->join, 0);
+}
+
+// Two concurrent scans fit when both grids (one CTA per (sequence, head) pair,
+// one CTA per SM) are resident together.
+bool scans_fit_together(const kda::Shape& s) { return 2L * s.N * s.H <= (long)kda::sm_count(); }
+
 }  // namespace
 
 namespace kda {
@@ -308,8 +353,17 @@ kda_status kda_chunk_fwd(const kda_problem* p, void* o, float* ht, void* saved, 
         if (e != cudaSuccess) return cuda_fail(e, "prep");
         e = traced("k_prep_wide", cs, [&] { return kda::launch_prep_wide(s, (int)p->gate, p->q, p->k, p->v, p->beta, p->g, t, f, cs); });
         if (e != cudaSuccess) return cuda_fail(e, "prep (wide chunks)");
-        e = traced("k_fwd_scan_tc", cs, [&] { return kda::launch_fwd_scan_tc(s, save ? 3 : 1, p->h0, t, f, o, ht, cs); });
+        // policy A: outputs and saved S, R from one scan, or (when the SMs allow) the output
+        // scan and the S, R scan side by side
+        Side* sd = (save && scans_fit_together(s)) ? side_stream() : nullptr;
+        if (sd) {
+            if ((e = side_fork(sd, cs)) != cudaSuccess) return cuda_fail(e, "side stream");
+            e = traced("k_fwd_scan_tc_save", sd->st, [&] { return kda::launch_fwd_scan_tc(s, 2, p->h0, t, f, nullptr, nullptr, sd->st); });
+            if (e != cudaSuccess) return cuda_fail(e, "forward scan (saved states)");
+        }
+        e = traced("k_fwd_scan_tc", cs, [&] { return kda::launch_fwd_scan_tc(s, (save && !sd) ? 3 : 1, p->h0, t, f, o, ht, cs); });
         if (e != cudaSuccess) return cuda_fail(e, "forward scan");
+        if (sd && (e = side_join(sd, cs)) != cudaSuccess) return cuda_fail(e, "side stream");
         return KDA_OK;
     }
     kda::Fwd f;
@@ -371,16 +425,25 @@ kda_status kda_chunk_bwd(const kda_problem* p, const void* dout, const float* dh
         const int gate = (int)p->gate;
         cudaError_t e = traced("k_table", cs, [&] { return kda::launch_table(s, p->B, p->T, p->cu_seqlens, t, cs); });
         if (e != cudaSuccess) return cuda_fail(e, "chunk table");
+        Side* sd = nullptr;
         if (!save) {
             e = traced("k_prep_tc", cs, [&] { return kda::launch_prep_tc(s, gate, 1, p->q, p->k, p->v, p->beta, p->g, t, f, cs); });
             if (e != cudaSuccess) return cuda_fail(e, "prep (recompute)");
             e = traced("k_prep_wide", cs, [&] { return kda::launch_prep_wide(s, gate, p->q, p->k, p->v, p->beta, p->g, t, f, cs); });
             if (e != cudaSuccess) return cuda_fail(e, "prep (recompute, wide chunks)");
-            e = traced("k_fwd_scan_tc_recompute", cs, [&] { return kda::launch_fwd_scan_tc(s, 2, p->h0, t, f, nullptr, nullptr, cs); });
+            // the S, R recompute and the reverse scan need only the prep: side by side
+            sd = side_stream();
+            cudaStream_t rs = cs;
+            if (sd) {
+                if ((e = side_fork(sd, cs)) != cudaSuccess) return cuda_fail(e, "side stream");
+                rs = sd->st;
+            }
+            e = traced("k_fwd_scan_tc_recompute", rs, [&] { return kda::launch_fwd_scan_tc(s, 2, p->h0, t, f, nullptr, nullptr, rs); });
             if (e != cudaSuccess) return cuda_fail(e, "forward scan (recompute)");
         }
         e = traced("k_bwd_scan_tc", cs, [&] { return kda::launch_bwd_scan_tc(s, dout, dht, t, f, b, dh0, cs); });
         if (e != cudaSuccess) return cuda_fail(e, "reverse scan");
+        if (sd && (e = side_join(sd, cs)) != cudaSuccess) return cuda_fail(e, "side stream");
         e = traced("k_bwd_consumer_tc", cs, [&] { return kda::launch_bwd_consumer_tc(s, gate, p->q, p->k, p->v, p->beta, p->g, dout, t, f, b, dq, dk, dv, dbeta, dg, cs); });
         if (e != cudaSuccess) return cuda_fail(e, "consumer");
         if (gate != KDA_GATE_NONE) {

@@ -457,28 +457,35 @@ constexpr int NB_AS = 1;           // S^T staged for D1
 constexpr int NB_AR = 2;           // R^T staged for the state update and the output
 constexpr int NB_C = 3;            //                compute warps only
 
-// Shared-memory map (bytes from the 1024-aligned base): the B operands only.
-constexpr int OFF_STAGE = 0;                 // two stages
-constexpr int STG_WQ = 0;                    // [W ; Q_g] as one K-major [128][128] tile  32 KB
-constexpr int STG_KG = 32768;                // F   [64][128]  16 KB (read MN-major)
-constexpr int STG_AQ = 49152;                // C_q [64][64]    8 KB
-constexpr int STG_BYTES = 57344;
-constexpr int OFF_OST = OFF_STAGE + 2 * STG_BYTES;   // output staging, 2 x [64][128] bf16 tile images, 32 KB
-// recompute mode (S and R saved, no output): the same region holds the S and R tile images of
-// two chunks, written to HBM by one bulk copy each
-constexpr int OFF_HST = OFF_OST;                       // 2 x S [128][128] bf16, 64 KB
-constexpr int OFF_RST = OFF_HST + 2 * D * D * 2;       // 2 x R [64][128] bf16, 32 KB
-// lambda [128] fp32, per-warp transpose staging (8 x 1280 B), barriers: after the staging the
-// mode uses (a smaller map leaves more of the SM's shared storage to the L1 cache)
+// Shared-memory map per mode (bytes from the 1024-aligned base): two operand stages (B operands
+// only), the staging the mode stores from, then lambda [128] fp32, per-warp transpose staging
+// (8 x 1280 B) and barriers. A smaller map leaves more of the SM's shared storage to the L1
+// cache, which carries the U loads of every chunk.
+//   mode 1 (output):        stage = [W ; Q_g] as one K-major [128][128] tile (32 KB), F [64][128]
+//                           (16 KB, read MN-major), C_q [64][64] (8 KB); two [64][128] output tile
+//                           images for the TMA stores
+//   mode 2 (S, R):          stage = W [64][128] (16 KB), F; S and R tile images of two chunks
+//   mode 3 (output, S, R):  stage as mode 1; S and R of one chunk; outputs stored from registers
+// S and R go to HBM by one bulk copy each.
 template <int MODE>
 struct ScanMap {
-    static constexpr int LAM = (MODE == 2) ? OFF_RST + 2 * BT * D * 2 : OFF_OST + 2 * BT * D * 2;
+    static constexpr bool OUT = (MODE & 1) != 0;
+    static constexpr int WROWS = OUT ? 2 * BT : BT;             // rows of the [W ; Q_g] (or W) tile
+    static constexpr int KG = WROWS * D * 2;                    // F
+    static constexpr int AQ = KG + BT * D * 2;                  // C_q (output modes)
+    static constexpr int STG = OUT ? AQ + BT * BT * 2 : AQ;     // bytes of one stage
+    static constexpr int NOST = (MODE == 1) ? 2 : 0;            // output staging tiles
+    static constexpr int NSR = (MODE == 2) ? 2 : (MODE == 3) ? 1 : 0;   // S/R staging pairs
+    static constexpr int OST = 2 * STG;
+    static constexpr int HST = OST + NOST * BT * D * 2;         // S [128][128] bf16 each
+    static constexpr int RST = HST + NSR * D * D * 2;           // R [64][128] bf16 each
+    static constexpr int LAM = RST + NSR * BT * D * 2;
     static constexpr int TST = LAM + 512;
     static constexpr int BAR = TST + 8 * 1280;
     static constexpr int SMEM = BAR + 64 + 1024;
     static_assert(SMEM <= 232448, "scan shared memory above the per-block limit");
+    static_assert(OST % 1024 == 0, "swizzled TMA stores need 1024-byte aligned tiles");
 };
-static_assert(OFF_OST % 1024 == 0, "swizzled TMA stores need 1024-byte aligned tiles");
 
 // TMEM columns: S^T fp32 [0,128); two buffers [D1 | O^T] of 128 columns at
 // [128,256) and [256,384), where one N = 128 pass S^T [W ; Q_g]^T gives D1 = S^T W^T
@@ -492,19 +499,22 @@ constexpr int T_DO = 128, T_AS = 384, T_AR = 448;
 // copies; one thread; completion arrives on `full` as transaction bytes.
 template <int MODE>
 __device__ __forceinline__ void fscan_fill(uint32_t stg, const FwdTC& f, size_t ch, uint64_t* full) {
+    using M = ScanMap<MODE>;
     constexpr uint32_t TILE = BT * D * 2, TQ = BT * BT * 2;
-    tc::mbar_arrive_expect_tx(full, (MODE & 1) ? 3 * TILE + TQ : 2 * TILE);
-    // W in rows 0..63 and Q_g in rows 64..127 of each 64-column atom block
+    tc::mbar_arrive_expect_tx(full, M::OUT ? 3 * TILE + TQ : 2 * TILE);
     const unsigned char* w = reinterpret_cast<const unsigned char*>(f.W + ch * BT * D);
-    tc::bulk_g2s(stg + STG_WQ, w, TILE / 2, full);
-    tc::bulk_g2s(stg + STG_WQ + 2 * BT * 128, w + TILE / 2, TILE / 2, full);
-    tc::bulk_g2s(stg + STG_KG, f.KG + ch * BT * D, TILE, full);
-    if (MODE & 1) {
+    if (M::OUT) {
+        // W in rows 0..63 and Q_g in rows 64..127 of each 64-column atom block
         const unsigned char* qg = reinterpret_cast<const unsigned char*>(f.QG + ch * BT * D);
-        tc::bulk_g2s(stg + STG_WQ + BT * 128, qg, TILE / 2, full);
-        tc::bulk_g2s(stg + STG_WQ + 3 * BT * 128, qg + TILE / 2, TILE / 2, full);
-        tc::bulk_g2s(stg + STG_AQ, f.AQK + ch * BT * BT, TQ, full);
+        tc::bulk_g2s(stg, w, TILE / 2, full);
+        tc::bulk_g2s(stg + 2 * BT * 128, w + TILE / 2, TILE / 2, full);
+        tc::bulk_g2s(stg + BT * 128, qg, TILE / 2, full);
+        tc::bulk_g2s(stg + 3 * BT * 128, qg + TILE / 2, TILE / 2, full);
+        tc::bulk_g2s(stg + M::AQ, f.AQK + ch * BT * BT, TQ, full);
+    } else {
+        tc::bulk_g2s(stg, w, TILE, full);   // the W tile image as it is
     }
+    tc::bulk_g2s(stg + M::KG, f.KG + ch * BT * D, TILE, full);
 }
 
 // The output of a full chunk from its staging tile (a [64][128] tile image) to
@@ -517,20 +527,20 @@ __device__ __forceinline__ void fscan_tma_out(const CUtensorMap* tmo, uint32_t o
     }
 }
 
-// A tail chunk's output rows [ib, ib+32) straight from O^T in TMEM (this thread:
-// value column vcol), rows >= len skipped.
+// Output rows [ib, ib+32) of a chunk straight from O^T in TMEM (this thread: value
+// column vcol), 16 rows at a time, rows >= len skipped.
 __device__ __forceinline__ void fscan_store_tail(uint32_t tl_o, int len, int tok0, int H, int h, int ib, int quad,
                                                  int lane, bf16* tst, bf16* __restrict__ o) {
-    float ov[2][16];
-    tc::tmem_ld16(tl_o + ib, ov[0]);
-    tc::tmem_ld16(tl_o + ib + 16, ov[1]);
-    tc::tmem_wait_ld();
-#pragma unroll
+#pragma unroll 1
     for (int cq = 0; cq < 32; cq += 16) {
         const int r0 = ib + cq;
-        if (r0 < len)
-            tc::warp_store_t16(tst, ov[cq / 16], o + ((size_t)(tok0 + r0) * H + h) * D + 32 * quad, (size_t)H * D,
-                               len - r0, lane);
+        if (r0 < len) {
+            float ov[16];
+            tc::tmem_ld16(tl_o + r0, ov);
+            tc::tmem_wait_ld();
+            tc::warp_store_t16(tst, ov, o + ((size_t)(tok0 + r0) * H + h) * D + 32 * quad, (size_t)H * D, len - r0,
+                               lane);
+        }
     }
 }
 
@@ -632,66 +642,53 @@ __device__ __forceinline__ void fscan_compute(const Shape& s, const float* __res
         tc::tmem_wait_st();
         // 3. R^T = U^T - D1 -> bf16 A operand (TMEM) of the state update and the output
         wait_one(&bar[0], it & 1);
-        float rv[2][16];
-        tc::tmem_ld16(tl + T_DO + 128 * stage + ib, rv[0]);
-        tc::tmem_ld16(tl + T_DO + 128 * stage + ib + 16, rv[1]);
-        tc::tmem_wait_ld();
+        uint32_t rp[16];   // R^T rows ib.. of this value column, bf16 pairs (kept for the saved R)
         {
-            uint32_t pw[16];
+            float rv[2][16];
+            tc::tmem_ld16(tl + T_DO + 128 * stage + ib, rv[0]);
+            tc::tmem_ld16(tl + T_DO + 128 * stage + ib + 16, rv[1]);
+            tc::tmem_wait_ld();
 #pragma unroll
             for (int cq = 0; cq < 2; ++cq) {
 #pragma unroll
                 for (int jj = 0; jj < 16; ++jj) rv[cq][jj] = u[16 * cq + jj] - rv[cq][jj];
 #pragma unroll
-                for (int jj = 0; jj < 8; ++jj) pw[8 * cq + jj] = tc::pack_bf16(rv[cq][2 * jj], rv[cq][2 * jj + 1]);
+                for (int jj = 0; jj < 8; ++jj) rp[8 * cq + jj] = tc::pack_bf16(rv[cq][2 * jj], rv[cq][2 * jj + 1]);
             }
-            tc::tmem_st16u(tl + T_AR + ib / 2, pw);
+            tc::tmem_st16u(tl + T_AR + ib / 2, rp);
         }
         tc::tmem_wait_st();
         tc::fence_before_sync();
         tc::named_sync(NB_AR, ST_ALL);
         // 4. while the state update runs: the saved S and R, the output of chunk c-1 (one output
         //    barrier per TMEM buffer, so the commit of this chunk's output cannot be taken for it)
-        if (MODE == 2) {
-            // S (from the bf16 S^T operand still in TMEM) and R as tile images into staging
-            // buffer it&1; the issuer copies them to HBM after the next hand-over
-            bf16* hs = reinterpret_cast<bf16*>(base + OFF_HST) + (it & 1) * D * D;
-            bf16* rs = reinterpret_cast<bf16*>(base + OFF_RST) + (it & 1) * BT * D;
+        if (MODE & 2) {
+            // R and S (from the bf16 S^T operand still in TMEM) as tile images into their staging
+            // buffer; the issuer copies them to HBM after the next hand-over
+            const int sbuf = (ScanMap<MODE>::NSR == 2) ? (it & 1) : 0;
+            uint16_t* hs = reinterpret_cast<uint16_t*>(base + ScanMap<MODE>::HST) + sbuf * D * D;
+            uint16_t* rs = reinterpret_cast<uint16_t*>(base + ScanMap<MODE>::RST) + sbuf * BT * D;
+            const uint16_t* r16 = reinterpret_cast<const uint16_t*>(rp);
 #pragma unroll
+            for (int j = 0; j < 32; ++j) rs[tile_el(BT, ib + j, vcol)] = r16[j];
+#pragma unroll 1
             for (int hq = 0; hq < 2; ++hq) {
                 float pv[16];
                 tc::tmem_ld16(tl + T_AS + kb / 2 + 16 * hq, pv);
                 tc::tmem_wait_ld();
                 const uint16_t* p16 = reinterpret_cast<const uint16_t*>(pv);
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    reinterpret_cast<uint16_t*>(hs)[tile_el(D, kb + 32 * hq + j, vcol)] = p16[j];
+                for (int j = 0; j < 32; ++j) hs[tile_el(D, kb + 32 * hq + j, vcol)] = p16[j];
             }
-#pragma unroll
-            for (int j = 0; j < 32; ++j) rs[tile_el(BT, ib + j, vcol)] = __float2bfloat16_rn(rv[j >> 4][j & 15]);
             tc::fence_async_smem();
-        } else if (MODE & 2) {
-            // the bf16 S^T of this chunk is still in its TMEM operand buffer
-#pragma unroll
-            for (int hq = 0; hq < 2; ++hq) {
-                float pv[16];
-                tc::tmem_ld16(tl + T_AS + kb / 2 + 16 * hq, pv);
-                tc::tmem_wait_ld();
-                const uint32_t* pw = reinterpret_cast<const uint32_t*>(pv);
-                tc::warp_store_t16_img_packed(tst, pw, f.HS + ch * D * D, D, kb + 32 * hq, 32 * quad, lane);
-                tc::warp_store_t16_img_packed(tst, pw + 8, f.HS + ch * D * D, D, kb + 32 * hq + 16, 32 * quad, lane);
-            }
-#pragma unroll
-            for (int cq = 0; cq < 32; cq += 16)
-                tc::warp_store_t16_img(tst, rv[cq / 16], f.R + ch * BT * D, BT, ib + cq, 32 * quad, lane);
         }
         if ((MODE & 1) && it > 0) {
             // output of chunk c-1: a full chunk goes to staging tile (it-1)&1 (stored by the
             // issuer after the next hand-over), a tail chunk straight to HBM
             wait_one(&bar[2 + ((it - 1) & 1)], ((it - 1) >> 1) & 1);
             const uint32_t to = tl + T_DO + 128 * ((it - 1) & 1) + 64;
-            if (lenp == BT)
-                fscan_stage_out(to, reinterpret_cast<bf16*>(base + OFF_OST) + ((it - 1) & 1) * BT * D, ib, vcol);
+            if (MODE == 1 && lenp == BT)
+                fscan_stage_out(to, reinterpret_cast<bf16*>(base + ScanMap<MODE>::OST) + ((it - 1) & 1) * BT * D, ib, vcol);
             else
                 fscan_store_tail(to, lenp, tok0p, H, h, ib, quad, lane, tst, o);
         }
@@ -705,8 +702,8 @@ __device__ __forceinline__ void fscan_compute(const Shape& s, const float* __res
             // the last output: staging tile last&1 (stored by the issuer at the end) or HBM
             wait_one(&bar[2 + (last & 1)], (last >> 1) & 1);
             const uint32_t to = tl + T_DO + 128 * (last & 1) + 64;
-            if (lenp == BT)
-                fscan_stage_out(to, reinterpret_cast<bf16*>(base + OFF_OST) + (last & 1) * BT * D, ib, vcol);
+            if (MODE == 1 && lenp == BT)
+                fscan_stage_out(to, reinterpret_cast<bf16*>(base + ScanMap<MODE>::OST) + (last & 1) * BT * D, ib, vcol);
             else
                 fscan_store_tail(to, lenp, tok0p, H, h, ib, quad, lane, tst, o);
         }
@@ -736,16 +733,17 @@ __device__ __forceinline__ void fscan_issue(const Shape& s, const Table& t, cons
     const uint32_t aS = tb + T_AS, aR = tb + T_AR;   // A operands in TMEM
     for (int c = c0; c < c1; ++c) {
         const int it = c - c0, stage = it & 1;
-        const uint32_t stg = sb + OFF_STAGE + stage * STG_BYTES;
+        const uint32_t stg = sb + stage * ScanMap<MODE>::STG;
         const uint32_t tD = tb + T_DO + 128 * stage;
         tc::named_sync(NB_AS, ST_ALL);
         tc::fence_after_sync();
         if (!tc::mbar_wait(&full[stage], (it >> 1) & 1) && lane == 0) atomicOr(t.err, 2);
         {
             // [D1 | O] = S^T [W ; Q_g]^T (D1 alone without the output)
-            const uint64_t dWQ = tc::sdesc(stg + STG_WQ);
+            const uint64_t dWQ = tc::sdesc(stg);
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) tc::mma_bf16_ts_w(tD, aS + 8 * ks, tc::kstep_k(dWQ, 2 * BT, ks), i1, ks > 0);
+            for (int ks = 0; ks < 8; ++ks)
+                tc::mma_bf16_ts_w(tD, aS + 8 * ks, tc::kstep_k(dWQ, ScanMap<MODE>::WROWS, ks), i1, ks > 0);
             tc::mma_commit_w(&bar[0]);
         }
         if (lane == 0) {
@@ -758,39 +756,47 @@ __device__ __forceinline__ void fscan_issue(const Shape& s, const Table& t, cons
                                                  : tc::mbar_wait(&bar[1], (it - 1) & 1);
                     if (!done) atomicOr(t.err, 2);
                 }
-                fscan_fill<MODE>(sb + OFF_STAGE + (stage ^ 1) * STG_BYTES, f, (size_t)(c + 1) * H + h,
+                fscan_fill<MODE>(sb + (stage ^ 1) * ScanMap<MODE>::STG, f, (size_t)(c + 1) * H + h,
                                  &full[stage ^ 1]);
                 ++filled;
             }
         }
-        // the output of chunk c-2 (a full chunk), staged by the compute warps during chunk c-1
-        if ((MODE & 1) && it >= 2 && pl == BT) fscan_tma_out(tmo, sb + OFF_OST + (it & 1) * BT * D * 2, pt, h, lane);
-        // recompute mode: S and R of chunk c-1, staged during chunk c-1
-        if (MODE == 2 && it >= 1 && lane == 0) {
+        // S and R of chunk c-1, staged during chunk c-1 (the older bulk group of this iteration)
+        if ((MODE & 2) && it >= 1 && lane == 0) {
             const size_t cp = (size_t)(c - 1) * H + h;
-            tc::bulk_s2g(f.HS + cp * D * D, sb + OFF_HST + ((it - 1) & 1) * D * D * 2, D * D * 2);
-            tc::bulk_s2g(f.R + cp * BT * D, sb + OFF_RST + ((it - 1) & 1) * BT * D * 2, BT * D * 2);
+            const int sbuf = (ScanMap<MODE>::NSR == 2) ? ((it - 1) & 1) : 0;
+            tc::bulk_s2g(f.HS + cp * D * D, sb + ScanMap<MODE>::HST + sbuf * D * D * 2, D * D * 2);
+            tc::bulk_s2g(f.R + cp * BT * D, sb + ScanMap<MODE>::RST + sbuf * BT * D * 2, BT * D * 2);
             tc::bulk_commit();
         }
-        if ((MODE & 1) && it >= 1) {   // extent of chunk c-1, whose output is stored next iteration
+        // the output of chunk c-2 (a full chunk), staged by the compute warps during chunk c-1
+        const bool o_out = MODE == 1 && it >= 2 && pl == BT;
+        if (o_out) fscan_tma_out(tmo, sb + ScanMap<MODE>::OST + (it & 1) * BT * D * 2, pt, h, lane);
+        if (MODE == 1 && it >= 1) {   // extent of chunk c-1, whose output is stored next iteration
             pl = __ldg(t.chunk_len + c - 1);
             pt = __ldg(t.chunk_tok0 + c - 1);
         }
-        // the staging tile stored during chunk c-1 is rewritten after this hand-over; the one
-        // stored just now may still be read (it is rewritten during chunk c+1)
-        if (lane == 0) tc::bulk_wait_read_prev();
+        // the staging tiles stored during chunk c-1 are rewritten after this hand-over; the output
+        // tile stored just now may still be read (it is rewritten during chunk c+1), and so may a
+        // double-buffered S/R pair; a single S/R pair is rewritten after this hand-over
+        if (lane == 0) {
+            if (ScanMap<MODE>::NSR == 1)
+                tc::bulk_wait_read();
+            else
+                tc::bulk_wait_read_prev();
+        }
         __syncwarp();
         tc::named_sync(NB_AR, ST_ALL);
         tc::fence_after_sync();
         // S^T += R^T F first (it gates the next chunk), then O^T += R^T C_q^T
         {
-            const uint64_t dF = tc::sdesc_mn(stg + STG_KG, BT * 128, 0);
+            const uint64_t dF = tc::sdesc_mn(stg + ScanMap<MODE>::KG, BT * 128, 0);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) tc::mma_bf16_ts_w(tb, aR + 8 * ks, tc::kstep_mn(dF, ks), i128m, 1);
             tc::mma_commit_w(&bar[1]);
         }
         if (MODE & 1) {
-            const uint64_t dA = tc::sdesc(stg + STG_AQ);
+            const uint64_t dA = tc::sdesc(stg + ScanMap<MODE>::AQ);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) tc::mma_bf16_ts_w(tD + 64, aR + 8 * ks, tc::kstep_k(dA, BT, ks), i64, 1);
             tc::mma_commit_w(&bar[2 + stage]);
@@ -819,7 +825,7 @@ __global__ void __launch_bounds__(ST_ALL, 1)
         for (int i = 0; i < 6; ++i) tc::mbar_init(&bar[i], 1);
         tc::fence_mbar_init();
         if (c0 < c1) {
-            fscan_fill<MODE>(sb + OFF_STAGE, f, (size_t)c0 * s.H + h, &full[0]);
+            fscan_fill<MODE>(sb, f, (size_t)c0 * s.H + h, &full[0]);
             filled = 1;
         }
     }
@@ -840,21 +846,23 @@ __global__ void __launch_bounds__(ST_ALL, 1)
         for (; waited < filled; ++waited) tc::mbar_wait(&full[waited & 1], (waited >> 1) & 1);
     tc::fence_before_sync();
     __syncthreads();
-    // recompute mode: S and R of the last chunk (staged after the issuer's loop ended)
-    if (MODE == 2 && issuer && c1 > c0 && (tid & 31) == 0) {
+    // S and R of the last chunk (staged after the issuer's loop ended)
+    if ((MODE & 2) && issuer && c1 > c0 && (tid & 31) == 0) {
         const int last = c1 - 1 - c0;
         const size_t cp = (size_t)(c1 - 1) * s.H + h;
-        tc::bulk_s2g(f.HS + cp * D * D, sb + OFF_HST + (last & 1) * D * D * 2, D * D * 2);
-        tc::bulk_s2g(f.R + cp * BT * D, sb + OFF_RST + (last & 1) * BT * D * 2, BT * D * 2);
+        const int sbuf = (ScanMap<MODE>::NSR == 2) ? (last & 1) : 0;
+        tc::bulk_s2g(f.HS + cp * D * D, sb + ScanMap<MODE>::HST + sbuf * D * D * 2, D * D * 2);
+        tc::bulk_s2g(f.R + cp * BT * D, sb + ScanMap<MODE>::RST + sbuf * BT * D * 2, BT * D * 2);
         tc::bulk_commit();
         tc::bulk_wait_all();
     }
     // the last two outputs (staged after the issuer's loop ended)
-    if ((MODE & 1) && issuer && c1 > c0) {
+    if (MODE == 1 && issuer && c1 > c0) {
         const int last = c1 - 1 - c0, lane = tid & 31;
-        if (last >= 1 && pl == BT) fscan_tma_out(&tmo, sb + OFF_OST + ((last - 1) & 1) * BT * D * 2, pt, h, lane);
+        constexpr int OST = ScanMap<MODE>::OST;
+        if (last >= 1 && pl == BT) fscan_tma_out(&tmo, sb + OST + ((last - 1) & 1) * BT * D * 2, pt, h, lane);
         if (t.chunk_len[c1 - 1] == BT)
-            fscan_tma_out(&tmo, sb + OFF_OST + (last & 1) * BT * D * 2, t.chunk_tok0[c1 - 1], h, lane);
+            fscan_tma_out(&tmo, sb + OST + (last & 1) * BT * D * 2, t.chunk_tok0[c1 - 1], h, lane);
         if (lane == 0) tc::bulk_wait_all();
     }
     if (warp == 0) tc::tmem_dealloc(tb, 512);
@@ -883,7 +891,7 @@ cudaError_t run_scan(const Shape& s, const float* h0, Table t, FwdTC f, void* o,
     if (e != cudaSuccess) return e;
     CUtensorMap mo;
     memset(&mo, 0, sizeof(mo));
-    if ((MODE & 1) && !tmap_rows_bf16(&mo, o, s.Ttot, s.H, D)) return cudaErrorInvalidValue;
+    if (MODE == 1 && !tmap_rows_bf16(&mo, o, s.Ttot, s.H, D)) return cudaErrorInvalidValue;
     dim3 grid(s.N, s.H);
     k_fwd_scan_tc<MODE><<<grid, ST_ALL, ScanMap<MODE>::SMEM, st>>>(s, mo, h0, t, f, (bf16*)o, ht);
     return cudaGetLastError();
