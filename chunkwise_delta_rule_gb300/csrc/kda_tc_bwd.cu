@@ -13,7 +13,8 @@
 // go to HBM (bf16) for the consumer. C_q, A, Q_g and W are read as MN-major
 // operands from their tile images, staged by bulk copies.
 //
-// k_bwd_consumer_tc (a9-a12), one CTA per (chunk slot, head), 512 threads:
+// k_bwd_consumer_tc (a9-a12), persistent (one CTA per SM walks the (chunk slot, head)
+// units, loading the next unit's tiles while it finishes the current one), 512 threads:
 //     [H_q ; -D] = [dO ; P] R^T   (masked: inclusive / strict, sign of D)
 //     [dO S^T ; P S^T] = [dO ; P] S^T        F_bar^T = S+bar R^T
 //     [T_q ; T_e] = [H_q ; D] (K zeta)        (A operand read from TMEM)
@@ -323,25 +324,40 @@ __global__ void __launch_bounds__(ST_ALL, 1)
 }
 
 // ================================================== k_bwd_consumer_tc
+// Persistent: one CTA per SM walks the (chunk slot, head) units u = c * H + h,
+// u = blockIdx.x, blockIdx.x + gridDim.x, ...; the inputs of the next unit are
+// loaded while this one finishes (three groups, each on its own mbarrier):
+//   C:  k, q (SW128 rows), g (fp32 rows)       after this unit's F2 (last reader of C)
+//   X1: [R ; S], S+bar tile images             after this unit's phase-B MMAs
+//   X2: [dO ; P], v                            after this unit's dg (the F arrays overlap them)
 constexpr int CT = 512;   // 16 warps: four warps share each TMEM lane quarter and split columns
 constexpr int LG = D + 1;
-// region X (128 KB): phase A operands, then phase B operands, then final tiles
-constexpr int X_OP = 0;          // [dO ; P]   bf16 [128][128]   32 KB
-constexpr int X_RS = 32768;      // [R ; S]    bf16 [192][128]   48 KB
-constexpr int X_SB = 81920;      // S+bar      bf16 [128][128]   32 KB
+constexpr int LDR = CT - 32;   // the thread that finds the next unit and issues its loads
+// region X: phase A operands, then phase B operands, then the F-phase arrays
+constexpr int X_RS = 0;          // [R ; S]   bf16 [192][128]  48 KB   (X1)
+constexpr int X_SB = 49152;      // S+bar     bf16 [128][128]  32 KB   (X1)
+constexpr int X_OP = 81920;      // [dO ; P]  bf16 [128][128]  32 KB   (X2)
+constexpr int X_V = 114688;      // v         bf16 [64][128]   16 KB   (X2, SW128 rows)
 constexpr int X_EQ = 0;          // [E_a^T | Q_a^T] tf32 [128][128] 64 KB
 constexpr int X_KZ = 65536;      // (K zeta)^T tf32 [128][64]    32 KB
 constexpr int X_DH = 98304;      // [D ; H_q]^T tf32 [64][128]   32 KB
-constexpr int X_BYTES = 131072;
-constexpr int C_A = X_BYTES;                      // g (dense rows, as TMA lands them), then alpha
+constexpr int X_FD = X_OP;       // F phase: sDK [64][129] fp32, then sGQ [64][129] fp32
+constexpr int X_END = X_FD + 2 * BT * LG * 4;
+constexpr int X_SCR = 131072;    // cumsum: segment totals, maxima, minima [3][4][128] fp32 (dead F-array rows)
+constexpr int C_A = (X_END + 1023) & ~1023;       // g (dense rows, as TMA lands them), then alpha
                                                   // = 2^(G2 - c) at aidx(row, col), fp32 [64][128]
 constexpr int C_K = C_A + 4 * BT * D;             // k bf16 [64][128], SW128 rows (conflict-free row and column reads)
 constexpr int C_Q = C_K + 2 * BT * D;             // q bf16 [64][128], SW128 rows
 constexpr int C_MISC = C_Q + 2 * BT * D;          // small arrays (floats)
 constexpr int M_BETA = 0, M_C2 = 64, M_AL = 192, M_LAMB = 320, M_DBW = 448, M_ROWP = 512,
-              M_ENDP = 768, M_ROW = 1280, M_END = 1344;
+              M_ENDP = 768, M_ROW = 1280, M_META = 1344, M_ENDT = 1352, M_END = 1480;
 constexpr int C_BAR = C_MISC + 4 * M_END;
 constexpr int CONS_SMEM = C_BAR + 64 + 1024;
+static_assert(X_SB + D * D * 2 <= X_OP, "X1 tiles overlap the F arrays");
+static_assert(X_V + BT * D * 2 <= X_SCR && X_DH + BT * D * 4 <= X_SCR && X_SCR + 12 * D * 4 <= X_END, "X region");
+static_assert(X_OP % 1024 == 0 && X_V % 1024 == 0 && X_SB % 1024 == 0 && C_K % 1024 == 0 && C_Q % 1024 == 0,
+              "swizzled tiles need 1024-byte alignment");
+static_assert(CONS_SMEM <= 232448, "consumer shared memory above the per-block limit");
 
 __device__ __forceinline__ float bfx(const bf16* p) { return __bfloat162float(*p); }
 
@@ -355,12 +371,80 @@ __device__ __forceinline__ float ldsw(const unsigned char* tile, int r, int col)
     return __bfloat162float(*reinterpret_cast<const bf16*>(tile + tc::sw128_off(BT, r, col * 2)));
 }
 
+// The next unit of this CTA after u that has tokens and a narrow gate range
+// (-1 when none is left); its chunk extent through n and tok0.
+template <int GATE>
+__device__ __forceinline__ int cons_next(int u, int total, int H, const Table& t, const FwdTC& f, int& n, int& tok0) {
+    for (u += gridDim.x; u < total; u += gridDim.x) {
+        const int c = u / H;
+        n = t.chunk_len[c];
+        if (n > 0 && (GATE == 0 || f.WIDE[u] == 0)) {
+            tok0 = t.chunk_tok0[c];
+            return u;
+        }
+    }
+    n = 0;
+    tok0 = 0;
+    return -1;
+}
+
+// Load group C of unit (h, tok0): k, q by TMA in SW128 rows, g (per-channel gate) as fp32 rows.
+template <int GATE>
+__device__ __forceinline__ void cons_load_c(uint32_t sb, const CUtensorMap* tmk, const CUtensorMap* tmq,
+                                            const CUtensorMap* tmg, int h, int tok0, uint64_t* b) {
+    tc::mbar_arrive_expect_tx(b, 2 * BT * D * 2 + (GATE == 2 ? BT * D * 4 : 0));
+    tc::tma_load3(sb + C_K, tmk, 0, h, tok0, b);
+    tc::tma_load3(sb + C_K + 8192, tmk, 64, h, tok0, b);
+    tc::tma_load3(sb + C_Q, tmq, 0, h, tok0, b);
+    tc::tma_load3(sb + C_Q + 8192, tmq, 64, h, tok0, b);
+    if (GATE == 2) tc::tma_load3(sb + C_A, tmg, 0, h, tok0, b);
+}
+
+// Load group X1 of unit ch: R in rows 0..63 and S in rows 64..191 of each atom column of the
+// [R ; S] tile, S+bar as it is (tile images, one bulk copy per piece).
+__device__ __forceinline__ void cons_load_x1(uint32_t sb, const FwdTC& f, const BwdTC& bw, size_t ch, uint64_t* b) {
+    tc::mbar_arrive_expect_tx(b, BT * D * 2 + 2 * D * D * 2);
+    const unsigned char* R0 = reinterpret_cast<const unsigned char*>(f.R + ch * BT * D);
+    const unsigned char* S0 = reinterpret_cast<const unsigned char*>(f.HS + ch * D * D);
+    tc::bulk_g2s(sb + X_RS, R0, 8192, b);
+    tc::bulk_g2s(sb + X_RS + 24576, R0 + 8192, 8192, b);
+    tc::bulk_g2s(sb + X_RS + 8192, S0, 16384, b);
+    tc::bulk_g2s(sb + X_RS + 24576 + 8192, S0 + 16384, 16384, b);
+    tc::bulk_g2s(sb + X_SB, bw.SBP + ch * D * D, 32768, b);
+}
+
+// Load group X2 of unit (ch, h, tok0): dO (TMA) in rows 0..63 and P (tile image) in rows
+// 64..127 of each atom column of the [dO ; P] tile; v by TMA in SW128 rows. Rows past the
+// chunk end hold the following tokens (or zeros past the tensor); every use masks them or
+// only reaches rows that are never stored.
+__device__ __forceinline__ void cons_load_x2(uint32_t sb, const CUtensorMap* tmo, const CUtensorMap* tmv,
+                                             const BwdTC& bw, size_t ch, int h, int tok0, uint64_t* b) {
+    tc::mbar_arrive_expect_tx(b, 3 * BT * D * 2);
+    const unsigned char* P0 = reinterpret_cast<const unsigned char*>(bw.P + ch * BT * D);
+    tc::bulk_g2s(sb + X_OP + 8192, P0, 8192, b);
+    tc::bulk_g2s(sb + X_OP + 16384 + 8192, P0 + 8192, 8192, b);
+    tc::tma_load3(sb + X_OP, tmo, 0, h, tok0, b);
+    tc::tma_load3(sb + X_OP + 16384, tmo, 64, h, tok0, b);
+    tc::tma_load3(sb + X_V, tmv, 0, h, tok0, b);
+    tc::tma_load3(sb + X_V + 8192, tmv, 64, h, tok0, b);
+}
+
+// Waits for one load group (parity = groups already waited, counted by every thread) and
+// meets the CTA; false (and the device error bit) when any thread's wait ran out.
+__device__ __forceinline__ bool cons_wait(uint64_t* b, int& w, int32_t* err) {
+    const bool r = tc::mbar_wait(b, w & 1);
+    if (r) ++w;
+    const bool ok = __syncthreads_and(r) != 0;
+    if (!ok && threadIdx.x == 0) atomicOr(err, 2);
+    return ok;
+}
+
 template <int GATE>
 __global__ void __launch_bounds__(CT, 1)
     k_bwd_consumer_tc(Shape s, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmo, const __grid_constant__ CUtensorMap tmg,
-                      const bf16* __restrict__ v, const bf16* __restrict__ beta, const float* __restrict__ g,
-                      Table t, FwdTC f, BwdTC b, bf16* __restrict__ dq,
+                      const __grid_constant__ CUtensorMap tmv, const bf16* __restrict__ beta,
+                      const float* __restrict__ g, Table t, FwdTC f, BwdTC bw, bf16* __restrict__ dq,
                       bf16* __restrict__ dk, bf16* __restrict__ dv, bf16* __restrict__ dbeta,
                       float* __restrict__ dg) {
     extern __shared__ unsigned char smem_raw[];
@@ -378,184 +462,185 @@ __global__ void __launch_bounds__(CT, 1)
     float* sRowP = sm + M_ROWP;   // [4][64] partial <k_i, gamma E_bar_i>
     float* sEndP = sm + M_ENDP;   // [4][128] partial sum_j F_j . F_bar_j
     float* sRow = sm + M_ROW;     // [64] scalar-gate row sums
-    uint64_t* bar = reinterpret_cast<uint64_t*>(base + C_BAR);   // MMA completions
-    uint64_t* bld = bar + 1;                                       // input tiles
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 2);
+    float* sEndT = sm + M_ENDT;   // [128] endpoint terms of the last row of G_bar
+    int* sMeta = reinterpret_cast<int*>(sm + M_META);             // two slots {unit, n, tok0, -}
+    float* sDK = reinterpret_cast<float*>(base + X_FD);           // [64][129] beta*gamma*E_bar + Y_bar/gamma
+    float* sGQ = sDK + BT * LG;                                   // [64][129] G_bar
+    uint64_t* bar = reinterpret_cast<uint64_t*>(base + C_BAR);    // MMA completions
+    uint64_t* bldC = bar + 1;                                     // load groups C, X1, X2
+    uint64_t* bldX1 = bar + 2;
+    uint64_t* bldX2 = bar + 3;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 4);
     const uint32_t sb = tc::smem_u32(base);
 
-    const int c = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = warp & 3, grp = warp >> 2;
-    // the chunk's extent and flag, read together (one latency)
-    const int H = s.H;
-    const size_t ch = (size_t)c * H + h;
-    const int n = t.chunk_len[c];
-    const int tok0 = t.chunk_tok0[c];
-    const int wide = (GATE != 0) ? f.WIDE[ch] : 0;
-    if (n <= 0) return;
-    if (wide) return;  // wide gate range: fp32 CUDA-core consumers
+    const int H = s.H, total = s.NC * s.H;
     const float scale = s.scale;
+    int nC = 0, nX1 = 0, nX2 = 0;   // load groups issued (thread LDR)
+    int wC = 0, wX1 = 0, wX2 = 0;   // load groups waited for (every thread)
 
-    // beta (read now, stored to shared memory once the loads below are in flight)
-    const float beta_r = (tid < BT && tid < n) ? bfx(beta + (size_t)(tok0 + tid) * H + h) : 0.f;
-    // token-major inputs by TMA: k, q (SW128 rows), dO (rows 0..63 of the [dO ; P] tile), g (fp32
-    // rows). Rows past the chunk end hold the following tokens (or zeros past the tensor); every
-    // use below either masks them or only reaches rows that are never stored.
-    if (tid == 0) {
-        tc::mbar_init(bar, 1);
-        tc::mbar_init(bld, 1);
+    if (tid == LDR) {
+        for (int i = 0; i < 4; ++i) tc::mbar_init(&bar[i], 1);
         tc::fence_mbar_init();
-        // P, R, S and S+bar are tile images: one bulk copy per atom column of the
-        // [dO ; P] and [R ; S] tiles, one for S+bar
-        tc::mbar_arrive_expect_tx(bld, 6 * 8192 + (GATE == 2 ? BT * D * 4 : 0) + 2 * 16384 + 2 * 32768);
-        const unsigned char* P0 = reinterpret_cast<const unsigned char*>(b.P + ch * BT * D);
-        const unsigned char* R0 = reinterpret_cast<const unsigned char*>(f.R + ch * BT * D);
-        const unsigned char* S0 = reinterpret_cast<const unsigned char*>(f.HS + ch * D * D);
-        tc::bulk_g2s(sb + X_OP + 8192, P0, 8192, bld);
-        tc::bulk_g2s(sb + X_OP + 16384 + 8192, P0 + 8192, 8192, bld);
-        tc::bulk_g2s(sb + X_RS, R0, 8192, bld);
-        tc::bulk_g2s(sb + X_RS + 24576, R0 + 8192, 8192, bld);
-        tc::bulk_g2s(sb + X_RS + 8192, S0, 16384, bld);
-        tc::bulk_g2s(sb + X_RS + 24576 + 8192, S0 + 16384, 16384, bld);
-        tc::bulk_g2s(sb + X_SB, b.SBP + ch * D * D, 32768, bld);
-        tc::tma_load3(sb + C_K, &tmk, 0, h, tok0, bld);
-        tc::tma_load3(sb + C_K + 8192, &tmk, 64, h, tok0, bld);
-        tc::tma_load3(sb + C_Q, &tmq, 0, h, tok0, bld);
-        tc::tma_load3(sb + C_Q + 8192, &tmq, 64, h, tok0, bld);
-        tc::tma_load3(sb + X_OP, &tmo, 0, h, tok0, bld);
-        tc::tma_load3(sb + X_OP + 16384, &tmo, 64, h, tok0, bld);
-        if (GATE == 2) tc::tma_load3(sb + C_A, &tmg, 0, h, tok0, bld);
+        int n0 = 0, t0 = 0;
+        const int u0 = cons_next<GATE>((int)blockIdx.x - (int)gridDim.x, total, H, t, f, n0, t0);
+        sMeta[0] = u0;
+        sMeta[1] = n0;
+        sMeta[2] = t0;
+        if (u0 >= 0) {
+            const int h0 = u0 % H;
+            cons_load_c<GATE>(sb, &tmk, &tmq, &tmg, h0, t0, bldC);
+            cons_load_x1(sb, f, bw, (size_t)u0, bldX1);
+            cons_load_x2(sb, &tmo, &tmv, bw, (size_t)u0, h0, t0, bldX2);
+            nC = nX1 = nX2 = 1;
+        }
     }
     if (warp == 0) {
         tc::tmem_alloc(tslot, 512);
         tc::tmem_relinquish();
     }
-    // v stays in registers for dv; beta; the G tile for a scalar gate (or zeros)
-    constexpr int NU = BT * D / 8 / CT;
-    uint4 vr4[NU];
-#pragma unroll
-    for (int u = 0; u < NU; ++u) {
-        const int ci = tid + CT * u, r = ci >> 4, c8 = (ci & 15) * 8;
-        vr4[u] = make_uint4(0, 0, 0, 0);
-        if (r < n) vr4[u] = __ldg(reinterpret_cast<const uint4*>(v + ((size_t)(tok0 + r) * H + h) * D + c8));
-    }
-    if (GATE != 2) {
-        for (int idx = tid; idx < BT * D / 4; idx += CT) {
-            const int r = idx >> 5, c4 = (idx & 31) * 4;
-            const float x = (GATE == 1 && r < n) ? __ldg(g + (size_t)(tok0 + r) * H + h) : 0.f;
-            *reinterpret_cast<float4*>(sA + r * D + c4) = make_float4(x, x, x, x);
-        }
-    }
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tb = *tslot;
-    bool ok = wait_all(bld, 0, t.err);
-    if (!ok && tid == 0) tc::mbar_wait(bld, 0);   // let late tiles land before the CTA can leave
-    if (!ok) {   // (device error recorded; the host reports it)
-        tc::fence_before_sync();
-        __syncthreads();
-        if (warp == 0) tc::tmem_dealloc(tb, 512);
-        return;
-    }
-    // TMEM columns: [0,64) [H_q ; -D] -> [H_q ; D] ; [64,192) [dO S^T ; P S^T] ;
-    // [192,256) F_bar^T ; [256,384) [T_q ; T_e] ; [384,448) T_y^T
-    if (warp == 0) {
-        // [dO ; P] [R ; S]^T fills columns [0, 192) in one N = 192 pass (warp-uniform
-        // descriptors, one elected lane issuing)
-        const uint32_t i64 = tc::idesc_bf16(128, 64), i192 = tc::idesc_bf16(128, BT + D);
-        const uint64_t dOP = tc::sdesc(sb + X_OP), dRS = tc::sdesc(sb + X_RS), dSB = tc::sdesc(sb + X_SB);
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-            tc::mma_bf16_w(tb, tc::kstep_k(dOP, D, ks), tc::kstep_k(dRS, BT + D, ks), i192, ks > 0);
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-            tc::mma_bf16_w(tb + 192, tc::kstep_k(dSB, D, ks), tc::kstep_k(dRS, BT + D, ks), i64, ks > 0);
-        tc::mma_commit_w(bar);
-    }
-    // while the MMAs run: cumsum (4 segments of 16 rows per feature), anchors, alpha tile;
-    // rowsum(S .* S+bar) and <v_i, P_i>, dv = beta P from the staged tiles
-    if (tid < BT) sBeta[tid] = beta_r;   // visible after the barrier inside the cumsum
-    {
-        const int col = tid >> 2, seg = tid & 3;
-        float x[16];
-        float acc = 0.f;
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            const int row = 16 * seg + r;
-            acc += (row < n) ? sA[row * D + col] : 0.f;
-            x[r] = acc * LOG2E;
-        }
-        acc *= LOG2E;
-        float pre = __shfl_up_sync(0xffffffffu, acc, 1, 4);
-        if (seg < 1) pre = 0.f;
-        float t2 = __shfl_up_sync(0xffffffffu, acc + pre, 2, 4);
-        if (seg < 2) t2 = 0.f;
-        const float off = pre + t2;
-        float hi = -INFINITY, lo = INFINITY;
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            x[r] += off;
-            if (16 * seg + r < n) {
-                hi = fmaxf(hi, x[r]);
-                lo = fminf(lo, x[r]);
+    float beta_nx = 0.f;                // beta of the next unit (threads < BT), read during this one
+    int cand = 0, cn = 0, ct0 = 0, cw = 0;   // next-unit candidate and its table entries (thread LDR)
+
+    for (int k = 0;; ++k) {
+        const int* meta = sMeta + 4 * (k & 1);
+        const int u = meta[0];
+        if (u < 0) break;
+        const int n = meta[1], tok0 = meta[2];
+        const int c = u / H, h = u - c * H;
+        const size_t ch = (size_t)u;
+        if (tid == LDR) {   // table entries of the next candidate, used after the phase-B MMAs
+            cand = u + (int)gridDim.x;
+            if (cand < total) {
+                cn = __ldg(t.chunk_len + cand / H);
+                ct0 = __ldg(t.chunk_tok0 + cand / H);
+                cw = (GATE != 0) ? __ldg(f.WIDE + cand) : 0;
             }
         }
-        hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, 1));
-        hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, 2));
-        lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, 1));
-        lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, 2));
-        const float cc = (GATE == 0) ? 0.f : 0.5f * (hi + lo);
-        const float glast = __shfl_sync(0xffffffffu, x[15], (lane & ~3) | 3);
-        __syncthreads();   // every g read before alpha overwrites the tile at swizzled positions
-#pragma unroll
-        for (int r = 0; r < 16; ++r) sA[aidx(16 * seg + r, col)] = exp2f(x[r] - cc);
-        if (seg == 0) {
-            sC2[col] = exp2f(cc);
-            sAL[col] = exp2f(glast - cc);
+        const float beta_r =
+            (k == 0) ? ((tid < BT && tid < n) ? bfx(beta + (size_t)(tok0 + tid) * H + h) : 0.f) : beta_nx;
+        // the G tile for a scalar gate (or zeros): tile C_A is free since the previous unit's F2
+        if (GATE != 2) {
+            for (int idx = tid; idx < BT * D / 4; idx += CT) {
+                const int r = idx >> 5, c4 = (idx & 31) * 4;
+                const float x = (GATE == 1 && r < n) ? __ldg(g + (size_t)(tok0 + r) * H + h) : 0.f;
+                *reinterpret_cast<float4*>(sA + r * D + c4) = make_float4(x, x, x, x);
+            }
         }
-    }
-    if (tid < D) {
-        const int kr = tid;
-        float acc = 0.f;
+        if (tid < BT) sBeta[tid] = beta_r;
+        if (!cons_wait(bldC, wC, t.err)) break;
+        // cumsum (4 segments of 16 rows per feature, warps 4s..4s+3 hold segment s, one feature
+        // per lane), anchors, alpha tile (overlaps the X loads); segments meet in shared memory
+        {
+            const int col = tid & (D - 1), seg = tid >> 7;
+            float* xt = reinterpret_cast<float*>(base + X_SCR);   // [3][4][128] totals, maxima, minima
+            float x[16];
+            float acc = 0.f, hi = -INFINITY, lo = INFINITY;
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                const int row = 16 * seg + r;
+                acc += (row < n) ? sA[row * D + col] : 0.f;
+                x[r] = acc * LOG2E;
+                if (row < n) {
+                    hi = fmaxf(hi, x[r]);
+                    lo = fminf(lo, x[r]);
+                }
+            }
+            xt[seg * D + col] = acc * LOG2E;
+            xt[4 * D + seg * D + col] = hi;
+            xt[8 * D + seg * D + col] = lo;
+            __syncthreads();   // (also: every g read before alpha overwrites the tile at swizzled positions)
+            float off = 0.f, run = 0.f, hh = -INFINITY, ll = INFINITY;
+#pragma unroll
+            for (int s2 = 0; s2 < 4; ++s2) {
+                const float ts = xt[s2 * D + col];
+                if (s2 < seg) off = run + ts;
+                hh = fmaxf(hh, xt[4 * D + s2 * D + col] + run);
+                ll = fminf(ll, xt[8 * D + s2 * D + col] + run);
+                run += ts;
+            }
+            const float cc = (GATE == 0) ? 0.f : 0.5f * (hh + ll);
+#pragma unroll
+            for (int r = 0; r < 16; ++r) sA[aidx(16 * seg + r, col)] = exp2f(x[r] + off - cc);
+            if (seg == 0) {
+                sC2[col] = exp2f(cc);
+                sAL[col] = exp2f(run - cc);   // run: G2 at the chunk end
+            }
+        }
+        // groups X1 and X2: [R ; S], S+bar, [dO ; P], v
+        {
+            const bool r1 = tc::mbar_wait(bldX1, wX1 & 1);
+            const bool r2 = tc::mbar_wait(bldX2, wX2 & 1);
+            wX1 += r1;
+            wX2 += r2;
+            if (!__syncthreads_and(r1 && r2)) {
+                if (tid == 0) atomicOr(t.err, 2);
+                break;
+            }
+        }
+        // TMEM columns: [0,64) [H_q ; -D] -> [H_q ; D] ; [64,192) [dO S^T ; P S^T] ;
+        // [192,256) F_bar^T ; [256,384) [T_q ; T_e] (then the erase part of G_bar, key rows) ;
+        // [384,448) T_y^T
+        if (warp == 0) {
+            tc::fence_after_sync();
+            // [dO ; P] [R ; S]^T fills columns [0, 192) in one N = 192 pass (warp-uniform
+            // descriptors, one elected lane issuing)
+            const uint32_t i64 = tc::idesc_bf16(128, 64), i192 = tc::idesc_bf16(128, BT + D);
+            const uint64_t dOP = tc::sdesc(sb + X_OP), dRS = tc::sdesc(sb + X_RS), dSB = tc::sdesc(sb + X_SB);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+                tc::mma_bf16_w(tb, tc::kstep_k(dOP, D, ks), tc::kstep_k(dRS, BT + D, ks), i192, ks > 0);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+                tc::mma_bf16_w(tb + 192, tc::kstep_k(dSB, D, ks), tc::kstep_k(dRS, BT + D, ks), i64, ks > 0);
+            tc::mma_commit_w(bar);
+        }
+        // while the MMAs run: rowsum(S .* S+bar) and <v_i, P_i>, dv = beta P from the staged tiles
+        if (tid < D) {
+            const int kr = tid;
+            float acc = 0.f;
 #pragma unroll 4
-        for (int cc = 0; cc < 16; ++cc) {
-            const uint4 a = *reinterpret_cast<const uint4*>(base + X_RS + tc::sw128_off(BT + D, BT + kr, cc * 16));
-            const uint4 bb = *reinterpret_cast<const uint4*>(base + X_SB + tc::sw128_off(D, kr, cc * 16));
-            const bf16* pa = reinterpret_cast<const bf16*>(&a);
-            const bf16* pb = reinterpret_cast<const bf16*>(&bb);
+            for (int cc = 0; cc < 16; ++cc) {
+                const uint4 a = *reinterpret_cast<const uint4*>(base + X_RS + tc::sw128_off(BT + D, BT + kr, cc * 16));
+                const uint4 bb = *reinterpret_cast<const uint4*>(base + X_SB + tc::sw128_off(D, kr, cc * 16));
+                const bf16* pa = reinterpret_cast<const bf16*>(&a);
+                const bf16* pb = reinterpret_cast<const bf16*>(&bb);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc = fmaf(__bfloat162float(pa[e]), __bfloat162float(pb[e]), acc);
-        }
-        sLamb[kr] = acc;
-    }
-    static_assert(NU * CT == BT * 16, "dv pass follows the v load map");
-#pragma unroll
-    for (int u = 0; u < NU; ++u) {   // 16 threads per row, 8 values each (the v load map)
-        const int idx = tid + CT * u, r = idx >> 4, cc = idx & 15;
-        float acc = 0.f;
-        if (r < n) {
-            const size_t tok = (size_t)(tok0 + r) * H + h;
-            const float bt = sBeta[r];
-            const uint4 pp = *reinterpret_cast<const uint4*>(base + X_OP + tc::sw128_off(2 * BT, BT + r, cc * 16));
-            const uint4 vv = vr4[u];
-            const bf16* pp2 = reinterpret_cast<const bf16*>(&pp);
-            const bf16* vv2 = reinterpret_cast<const bf16*>(&vv);
-            uint32_t out[4];
-#pragma unroll
-            for (int e = 0; e < 8; e += 2) {
-                const float p0 = __bfloat162float(pp2[e]), p1 = __bfloat162float(pp2[e + 1]);
-                acc = fmaf(__bfloat162float(vv2[e]), p0, acc);
-                acc = fmaf(__bfloat162float(vv2[e + 1]), p1, acc);
-                out[e / 2] = tc::pack_bf16(bt * p0, bt * p1);
+                for (int e = 0; e < 8; ++e) acc = fmaf(__bfloat162float(pa[e]), __bfloat162float(pb[e]), acc);
             }
-            *reinterpret_cast<uint4*>(dv + tok * D + cc * 8) = make_uint4(out[0], out[1], out[2], out[3]);
+            sLamb[kr] = acc;
         }
 #pragma unroll
-        for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o, 16);
-        if (cc == 0) sDbw[r] = acc;
-    }
-    ok = wait_all(bar, 0, t.err);
-    if (ok) {
+        for (int uu = 0; uu < BT * 16 / CT; ++uu) {   // 16 threads per row, 8 values each
+            const int idx = tid + CT * uu, r = idx >> 4, cc = idx & 15;
+            float acc = 0.f;
+            if (r < n) {
+                const size_t tok = (size_t)(tok0 + r) * H + h;
+                const float bt = sBeta[r];
+                const uint4 pp = *reinterpret_cast<const uint4*>(base + X_OP + tc::sw128_off(2 * BT, BT + r, cc * 16));
+                const uint4 vv = *reinterpret_cast<const uint4*>(base + X_V + tc::sw128_off(BT, r, cc * 16));
+                const bf16* pp2 = reinterpret_cast<const bf16*>(&pp);
+                const bf16* vv2 = reinterpret_cast<const bf16*>(&vv);
+                uint32_t out[4];
+#pragma unroll
+                for (int e = 0; e < 8; e += 2) {
+                    const float p0 = __bfloat162float(pp2[e]), p1 = __bfloat162float(pp2[e + 1]);
+                    acc = fmaf(__bfloat162float(vv2[e]), p0, acc);
+                    acc = fmaf(__bfloat162float(vv2[e + 1]), p1, acc);
+                    out[e / 2] = tc::pack_bf16(bt * p0, bt * p1);
+                }
+                *reinterpret_cast<uint4*>(dv + tok * D + cc * 8) = make_uint4(out[0], out[1], out[2], out[3]);
+            }
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o, 16);
+            if (cc == 0) sDbw[r] = acc;
+        }
+        if (!wait_all(bar, 0, t.err)) break;
         tc::fence_after_sync();
         // ---- epilogue A: mask [H_q ; -D] into [H_q ; D] (scalar gate: fold the pairwise decay
         // alpha_i / alpha_j), keep it in TMEM as the A operand of [T_q ; T_e], and write its
@@ -588,12 +673,12 @@ __global__ void __launch_bounds__(CT, 1)
             const int kr = tid & (D - 1), kch = (kr >> 3) & 7;
             const uint32_t kbase = (uint32_t)((kr >> 6) * BT * 128 + (kr & 7) * 2);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int g = (tid >> 7) + 4 * u;   // tokens 4g .. 4g+3
+            for (int uq = 0; uq < 4; ++uq) {
+                const int gq = (tid >> 7) + 4 * uq;   // tokens 4gq .. 4gq+3
                 float kz[4], ea[4], qa[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const int j = 4 * g + e;
+                    const int j = 4 * gq + e;
                     const uint32_t off = kbase + j * 128 + ((kch ^ (j & 7)) << 4);
                     const float kv = __bfloat162float(*reinterpret_cast<const bf16*>(sK + off));
                     const float qv = __bfloat162float(*reinterpret_cast<const bf16*>(sQ + off));
@@ -603,9 +688,9 @@ __global__ void __launch_bounds__(CT, 1)
                     ea[e] = in ? sBeta[j] * kv * al : 0.f;
                     qa[e] = in ? scale * qv * al : 0.f;
                 }
-                *reinterpret_cast<float4*>(base + X_KZ + tc::sw128_off(D, kr, g * 16)) = make_float4(kz[0], kz[1], kz[2], kz[3]);
-                *reinterpret_cast<float4*>(base + X_EQ + tc::sw128_off(D, kr, g * 16)) = make_float4(ea[0], ea[1], ea[2], ea[3]);
-                *reinterpret_cast<float4*>(base + X_EQ + tc::sw128_off(D, kr, (16 + g) * 16)) =
+                *reinterpret_cast<float4*>(base + X_KZ + tc::sw128_off(D, kr, gq * 16)) = make_float4(kz[0], kz[1], kz[2], kz[3]);
+                *reinterpret_cast<float4*>(base + X_EQ + tc::sw128_off(D, kr, gq * 16)) = make_float4(ea[0], ea[1], ea[2], ea[3]);
+                *reinterpret_cast<float4*>(base + X_EQ + tc::sw128_off(D, kr, (16 + gq) * 16)) =
                     make_float4(qa[0], qa[1], qa[2], qa[3]);
             }
         }
@@ -624,14 +709,32 @@ __global__ void __launch_bounds__(CT, 1)
                 tc::mma_tf32_w(tb + 384, tc::kstep_k(dEQ, D, ks), tc::kstep_k(dDH, BT, ks), i64, ks > 0);
             tc::mma_commit_w(bar);
         }
-        ok = wait_all(bar, 1, t.err);
-    }
-    if (ok) {
+        if (!wait_all(bar, 1, t.err)) break;
         tc::fence_after_sync();
-        float* sDK = reinterpret_cast<float*>(base);              // [64][129] beta*gamma*E_bar + Y_bar/gamma
-        float* sGQ = sDK + BT * LG;                               // [64][129] G_bar (query and key-side parts)
-        float* sGE = sGQ + BT * LG;                               // [64][129] G_bar (erase part)
-        // ---- F1: rows of [T_q ; T_e] and [dO S^T ; P S^T]; four warps per lane quarter, 32 columns each
+        // the next unit: settle it (the candidate, else a walk over the table) and load its
+        // group X1 into the phase-A tiles, free since the phase-B MMAs completed
+        int nxt = -1;
+        if (tid == LDR) {
+            int nn = 0, nt = 0;
+            if (cand < total && cn > 0 && cw == 0) {
+                nxt = cand;
+                nn = cn;
+                nt = ct0;
+            } else if (cand < total) {
+                nxt = cons_next<GATE>(cand, total, H, t, f, nn, nt);
+            }
+            int* nm = sMeta + 4 * ((k + 1) & 1);
+            nm[0] = nxt;
+            nm[1] = nn;
+            nm[2] = nt;
+            if (nxt >= 0) {
+                cons_load_x1(sb, f, bw, (size_t)nxt, bldX1);
+                ++nX1;
+            }
+        }
+        // ---- F1: rows of [T_q ; T_e] and [dO S^T ; P S^T]; four warps per lane quarter, 32 columns
+        // each. Key rows keep the erase part of G_bar in TMEM over the T_e values they consumed
+        // (added to G_bar in F3, where no other thread writes those elements).
         {
             const int row = 32 * quad + lane, cb0 = grp * 32;
             const bool isQ = row < BT;
@@ -651,7 +754,8 @@ __global__ void __launch_bounds__(CT, 1)
 #pragma unroll
             for (int cb = 0; cb < 32; cb += 16) {
                 float tq[16], tp[16];
-                tc::tmem_ld16(tc::taddr(tb + 256, 32 * quad, cb0 + cb), tq);
+                const uint32_t tqa = tc::taddr(tb + 256, 32 * quad, cb0 + cb);
+                tc::tmem_ld16(tqa, tq);
                 tc::tmem_ld16(tc::taddr(tb + 64, 32 * quad, cb0 + cb), tp);
                 tc::tmem_wait_ld();
 #pragma unroll
@@ -669,13 +773,15 @@ __global__ void __launch_bounds__(CT, 1)
                         const float Et = fac * tq[jj] - gam * tp[jj];               // gamma * E_bar
                         const float kv = xq;
                         sDK[i * LG + kr] = bt * Et;
-                        sGE[i * LG + kr] = bt * kv * Et;
+                        tq[jj] = bt * kv * Et;                                      // erase part of G_bar
                         part = fmaf(kv, Et, part);
                     }
                 }
                 if (isQ) {
 #pragma unroll
                     for (int jj = 0; jj < 8; ++jj) packed[cb / 2 + jj] = tc::pack_bf16(tq[2 * jj], tq[2 * jj + 1]);
+                } else if (GATE != 0) {
+                    tc::tmem_st16(tqa, tq);
                 }
             }
             if (isQ) {
@@ -687,6 +793,7 @@ __global__ void __launch_bounds__(CT, 1)
                 }
             } else {
                 sRowP[grp * BT + i] = part;
+                if (GATE != 0) tc::tmem_wait_st();
             }
         }
         __syncthreads();
@@ -713,8 +820,23 @@ __global__ void __launch_bounds__(CT, 1)
             }
             sEndP[grp * D + kr] = endp;
         }
+        tc::fence_async_smem();   // the alpha tile's generic writes before the next g lands by TMA
         __syncthreads();
-        // ---- F3: dk, dbeta, dg
+        // k, q, g of the next unit into their tiles (last read in F2); its beta into registers
+        {
+            const int* nm = sMeta + 4 * ((k + 1) & 1);
+            const int nu = nm[0];
+            if (nu >= 0) {
+                const int nh = nu % H;
+                if (tid == LDR) {
+                    cons_load_c<GATE>(sb, &tmk, &tmq, &tmg, nh, nm[2], bldC);
+                    ++nC;
+                }
+                beta_nx = (tid < BT && tid < nm[1]) ? bfx(beta + (size_t)(nm[2] + tid) * H + nh) : 0.f;
+            }
+        }
+        // ---- F3: dk, dbeta; key rows add the erase part of G_bar; the endpoint terms of the last
+        // row (lambda rowsum(S .* S+bar) + sum_j F_j . F_bar_j), added to it in dg
         for (int idx = tid; idx < BT * D / 8; idx += CT) {
             const int r = idx >> 4, cc = idx & 15;
             if (r < n) {
@@ -729,10 +851,19 @@ __global__ void __launch_bounds__(CT, 1)
             dbeta[(size_t)(tok0 + tid) * H + h] = __float2bfloat16_rn(sRowP[tid] + sRowP[BT + tid] + sRowP[2 * BT + tid] +
                                                                       sRowP[3 * BT + tid] + sDbw[tid]);
         if (GATE != 0) {
-            if (tid < D) {
-                const float lam = sAL[tid] * sC2[tid];   // 2^G2_last
-                const float endp = lam * sLamb[tid] + sEndP[tid] + sEndP[D + tid] + sEndP[2 * D + tid] + sEndP[3 * D + tid];
-                sGQ[(n - 1) * LG + tid] += endp;
+            if (tid < D)
+                sEndT[tid] = sAL[tid] * sC2[tid] * sLamb[tid] + sEndP[tid] + sEndP[D + tid] + sEndP[2 * D + tid] +
+                             sEndP[3 * D + tid];
+            if (quad >= 2) {
+                const int i = 32 * quad + lane - BT, cb0 = grp * 32;
+                float ge[2][16];
+                tc::tmem_ld16(tc::taddr(tb + 256, 32 * quad, cb0), ge[0]);
+                tc::tmem_ld16(tc::taddr(tb + 256, 32 * quad, cb0 + 16), ge[1]);
+                tc::tmem_wait_ld();
+                if (i < n) {
+#pragma unroll
+                    for (int jj = 0; jj < 32; ++jj) sGQ[i * LG + cb0 + jj] += ge[jj >> 4][jj & 15];
+                }
             }
             __syncthreads();
             if (GATE == 2) {
@@ -745,7 +876,7 @@ __global__ void __launch_bounds__(CT, 1)
 #pragma unroll
                 for (int r = 15; r >= 0; --r) {
                     const int row = 16 * seg + r;
-                    acc += (row < n) ? sGQ[row * LG + col] + sGE[row * LG + col] : 0.f;
+                    acc += (row < n) ? sGQ[row * LG + col] + (row == n - 1 ? sEndT[col] : 0.f) : 0.f;
                     x[r] = acc;
                 }
                 float* sSeg = sEndP;   // [4][128]
@@ -761,7 +892,7 @@ __global__ void __launch_bounds__(CT, 1)
             } else {
                 for (int r = warp; r < BT; r += CT / 32) {
                     float xs = 0.f;
-                    for (int col = lane; col < D; col += 32) xs += sGQ[r * LG + col] + sGE[r * LG + col];
+                    for (int col = lane; col < D; col += 32) xs += sGQ[r * LG + col] + (r == n - 1 ? sEndT[col] : 0.f);
 #pragma unroll
                     for (int o = 16; o > 0; o >>= 1) xs += __shfl_xor_sync(0xffffffffu, xs, o);
                     if (lane == 0) sRow[r] = xs;
@@ -776,6 +907,23 @@ __global__ void __launch_bounds__(CT, 1)
                 }
             }
         }
+        // every read of the F arrays is done: group X2 of the next unit lands over them
+        tc::fence_async_smem();
+        tc::fence_before_sync();
+        __syncthreads();
+        if (tid == LDR) {
+            const int* nm = sMeta + 4 * ((k + 1) & 1);
+            if (nm[0] >= 0) {
+                cons_load_x2(sb, &tmo, &tmv, bw, (size_t)nm[0], nm[0] % H, nm[2], bldX2);
+                ++nX2;
+            }
+        }
+    }
+    // a load still in flight (only after a timeout) lands before the CTA leaves
+    if (tid == LDR) {
+        for (; wC < nC; ++wC) tc::mbar_wait(bldC, wC & 1);
+        for (; wX1 < nX1; ++wX1) tc::mbar_wait(bldX1, wX1 & 1);
+        for (; wX2 < nX2; ++wX2) tc::mbar_wait(bldX2, wX2 & 1);
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -788,14 +936,17 @@ cudaError_t run_consumer(const Shape& s, const void* q, const void* k, const voi
                          void* dv, void* dbeta, float* dg, cudaStream_t st) {
     cudaError_t e = set_smem_once<k_bwd_consumer_tc<GATE>>(CONS_SMEM);
     if (e != cudaSuccess) return e;
-    CUtensorMap mq, mk, mo, mg;
+    CUtensorMap mq, mk, mo, mg, mv;
     memset(&mg, 0, sizeof(mg));
     if (!tmap_rows_bf16(&mq, q, s.Ttot, s.H, D) || !tmap_rows_bf16(&mk, k, s.Ttot, s.H, D) ||
-        !tmap_rows_bf16(&mo, dout, s.Ttot, s.H, D) || (GATE == 2 && !tmap_rows_f32(&mg, g, s.Ttot, s.H, D)))
+        !tmap_rows_bf16(&mo, dout, s.Ttot, s.H, D) || !tmap_rows_bf16(&mv, v, s.Ttot, s.H, D) ||
+        (GATE == 2 && !tmap_rows_f32(&mg, g, s.Ttot, s.H, D)))
         return cudaErrorInvalidValue;
-    dim3 grid(s.NC, s.H);
-    k_bwd_consumer_tc<GATE><<<grid, CT, CONS_SMEM, st>>>(s, mq, mk, mo, mg, (const bf16*)v, (const bf16*)beta, g, t, f,
-                                                         b, (bf16*)dq, (bf16*)dk, (bf16*)dv, (bf16*)dbeta, dg);
+    const long units = (long)s.NC * s.H;
+    if (units <= 0) return cudaSuccess;
+    const int grid = (int)(units < sm_count() ? units : sm_count());   // one CTA per SM, persistent
+    k_bwd_consumer_tc<GATE><<<grid, CT, CONS_SMEM, st>>>(s, mq, mk, mo, mg, mv, (const bf16*)beta, g, t, f, b,
+                                                         (bf16*)dq, (bf16*)dk, (bf16*)dv, (bf16*)dbeta, dg);
     return cudaGetLastError();
 }
 
