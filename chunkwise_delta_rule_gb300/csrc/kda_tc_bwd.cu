@@ -349,8 +349,8 @@ constexpr int C_A = (X_END + 1023) & ~1023;       // g (dense rows, as TMA lands
 constexpr int C_K = C_A + 4 * BT * D;             // k bf16 [64][128], SW128 rows (conflict-free row and column reads)
 constexpr int C_Q = C_K + 2 * BT * D;             // q bf16 [64][128], SW128 rows
 constexpr int C_MISC = C_Q + 2 * BT * D;          // small arrays (floats)
-constexpr int M_BETA = 0, M_C2 = 64, M_AL = 192, M_LAMB = 320, M_DBW = 448, M_ROWP = 512,
-              M_ENDP = 768, M_ROW = 1280, M_META = 1344, M_ENDT = 1352, M_END = 1480;
+constexpr int M_BETA = 0, M_C2 = 64, M_AL = 192, M_DBW = 448, M_ROWP = 512,
+              M_ENDP = 768, M_ROW = 1280, M_META = 1344, M_ENDT = 1352, M_LAMP = 1480, M_END = 1992;
 constexpr int C_BAR = C_MISC + 4 * M_END;
 constexpr int CONS_SMEM = C_BAR + 64 + 1024;
 static_assert(X_SB + D * D * 2 <= X_OP, "X1 tiles overlap the F arrays");
@@ -457,7 +457,7 @@ __global__ void __launch_bounds__(CT, 1)
     float* sBeta = sm + M_BETA;
     float* sC2 = sm + M_C2;       // 2^c per feature
     float* sAL = sm + M_AL;       // 2^(G2_last - c) per feature
-    float* sLamb = sm + M_LAMB;   // rowsum(S .* S+bar) per key
+    float* sLamP = sm + M_LAMP;   // [4][128] partial rowsum(S .* S+bar) per key
     float* sDbw = sm + M_DBW;     // <v_i, P_i>
     float* sRowP = sm + M_ROWP;   // [4][64] partial <k_i, gamma E_bar_i>
     float* sEndP = sm + M_ENDP;   // [4][128] partial sum_j F_j . F_bar_j
@@ -504,7 +504,7 @@ __global__ void __launch_bounds__(CT, 1)
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tb = *tslot;
-    float beta_nx = 0.f;                // beta of the next unit (threads < BT), read during this one
+    bf16 beta_nx = __float2bfloat16_rn(0.f);   // beta of the next unit (threads < BT), read during this one
     int cand = 0, cn = 0, ct0 = 0, cw = 0;   // next-unit candidate and its table entries (thread LDR)
 
     for (int k = 0;; ++k) {
@@ -523,7 +523,7 @@ __global__ void __launch_bounds__(CT, 1)
             }
         }
         const float beta_r =
-            (k == 0) ? ((tid < BT && tid < n) ? bfx(beta + (size_t)(tok0 + tid) * H + h) : 0.f) : beta_nx;
+            (k == 0) ? ((tid < BT && tid < n) ? bfx(beta + (size_t)(tok0 + tid) * H + h) : 0.f) : __bfloat162float(beta_nx);
         // the G tile for a scalar gate (or zeros): tile C_A is free since the previous unit's F2
         if (GATE != 2) {
             for (int idx = tid; idx < BT * D / 4; idx += CT) {
@@ -600,20 +600,24 @@ __global__ void __launch_bounds__(CT, 1)
                 tc::mma_bf16_w(tb + 192, tc::kstep_k(dSB, D, ks), tc::kstep_k(dRS, BT + D, ks), i64, ks > 0);
             tc::mma_commit_w(bar);
         }
-        // while the MMAs run: rowsum(S .* S+bar) and <v_i, P_i>, dv = beta P from the staged tiles
-        if (tid < D) {
-            const int kr = tid;
-            float acc = 0.f;
-#pragma unroll 4
-            for (int cc = 0; cc < 16; ++cc) {
+        // while the MMAs run: rowsum(S .* S+bar) (key kr, a quarter of the values per thread) and
+        // <v_i, P_i>, dv = beta P from the staged tiles
+        {
+            const int kr = tid & (D - 1), q4 = tid >> 7;
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int cc = 4 * q4; cc < 4 * q4 + 4; ++cc) {
                 const uint4 a = *reinterpret_cast<const uint4*>(base + X_RS + tc::sw128_off(BT + D, BT + kr, cc * 16));
                 const uint4 bb = *reinterpret_cast<const uint4*>(base + X_SB + tc::sw128_off(D, kr, cc * 16));
                 const bf16* pa = reinterpret_cast<const bf16*>(&a);
                 const bf16* pb = reinterpret_cast<const bf16*>(&bb);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc = fmaf(__bfloat162float(pa[e]), __bfloat162float(pb[e]), acc);
+                for (int e = 0; e < 8; e += 2) {
+                    a0 = fmaf(__bfloat162float(pa[e]), __bfloat162float(pb[e]), a0);
+                    a1 = fmaf(__bfloat162float(pa[e + 1]), __bfloat162float(pb[e + 1]), a1);
+                }
             }
-            sLamb[kr] = acc;
+            sLamP[q4 * D + kr] = a0 + a1;
         }
 #pragma unroll
         for (int uu = 0; uu < BT * 16 / CT; ++uu) {   // 16 threads per row, 8 values each
@@ -832,7 +836,8 @@ __global__ void __launch_bounds__(CT, 1)
                     cons_load_c<GATE>(sb, &tmk, &tmq, &tmg, nh, nm[2], bldC);
                     ++nC;
                 }
-                beta_nx = (tid < BT && tid < nm[1]) ? bfx(beta + (size_t)(nm[2] + tid) * H + nh) : 0.f;
+                // kept as bf16 so the load stays in flight until the next unit starts
+                if (tid < BT) beta_nx = (tid < nm[1]) ? beta[(size_t)(nm[2] + tid) * H + nh] : __float2bfloat16_rn(0.f);
             }
         }
         // ---- F3: dk, dbeta; key rows add the erase part of G_bar; the endpoint terms of the last
@@ -852,8 +857,8 @@ __global__ void __launch_bounds__(CT, 1)
                                                                       sRowP[3 * BT + tid] + sDbw[tid]);
         if (GATE != 0) {
             if (tid < D)
-                sEndT[tid] = sAL[tid] * sC2[tid] * sLamb[tid] + sEndP[tid] + sEndP[D + tid] + sEndP[2 * D + tid] +
-                             sEndP[3 * D + tid];
+                sEndT[tid] = sAL[tid] * sC2[tid] * (sLamP[tid] + sLamP[D + tid] + sLamP[2 * D + tid] + sLamP[3 * D + tid]) +
+                             sEndP[tid] + sEndP[D + tid] + sEndP[2 * D + tid] + sEndP[3 * D + tid];
             if (quad >= 2) {
                 const int i = 32 * quad + lane - BT, cb0 = grp * 32;
                 float ge[2][16];
