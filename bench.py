@@ -76,11 +76,12 @@ def flops_model(case):
     return fwd * case.H, bwd * case.H, rec * case.H
 
 
-def kernel_work(case):
+def kernel_work(case, save=False):
     """Algorithmic work per launch of each library kernel: dense FLOPs (the
     products the kernel owns in the FLOP model) and bytes (every tensor the
     kernel must read or write once, at its stored precision), summed over
-    chunk x head with the exact chunk length n (d = dk = dv)."""
+    chunk x head with the exact chunk length n (d = dk = dv). Under the save
+    policy the forward prep also writes A for the backward."""
     d = case.K
     e = 2 if case.io == "bf16" else 4
     gb = {"channel": 4 * d, "scalar": 4, "none": 0}[case.gate]   # log-decay bytes per token
@@ -102,7 +103,8 @@ def kernel_work(case):
         fl["k_bwd_scan_tc"] += 6 * n * d * d + 4 * n * n * d
         fl["k_bwd_consumer_tc"] += 12 * n * n * d + 6 * n * d * d
         # tensor-core path: bf16 tiles W, F, Q_g, C_q, A, S, S+bar, R, P; fp32 U and G at the chunk end
-        by["k_prep_tc"] += 3 * n * d * e + n * gb + n * e + 3 * n * d * 2 + n * n * 2 + n * d * 4 + d * 4
+        by["k_prep_tc"] += (3 * n * d * e + n * gb + n * e + 3 * n * d * 2 + n * n * 2 + n * d * 4 + d * 4
+                            + (n * n * 2 if save else 0))
         by["k_fwd_scan_tc"] += 3 * n * d * 2 + n * n * 2 + n * d * 4 + d * 4 + n * d * e
         by["k_fwd_scan_tc_recompute"] += 2 * n * d * 2 + n * d * 4 + d * 4 + d * d * 2 + n * d * 2
         by["k_fwd_scan_tc_save"] += 2 * n * d * 2 + n * d * 4 + d * 4 + d * d * 2 + n * d * 2
@@ -330,7 +332,7 @@ def run_ours(args):
     pk = peaks()
     launches = sum(v[0] for v in kern.values())
     # dominant kernel and its roofline
-    work = kernel_work(case)
+    work = kernel_work(case, save=bool(save))
     dom = max(kern.items(), key=lambda kv: kv[1][1])[0] if kern else None
     roof = None
     if dom:
