@@ -488,6 +488,68 @@ def cpu_baseline(case_cpu):
                       f"recurrence + BPTT, {dt:.1f} s wall; tokens/s = token-heads / H / wall"}
 
 
+DECODE = dict(name="kda_decode_bf16", B=64, H=32, K=128, V=128)
+
+
+def run_decode(args):
+    """Decoding: one token for each of B sequences through the token-by-token
+    forward, the fp32 states updated in place (the serving step). The state
+    traffic (read + write, 128 KB per (sequence, head)) dominates; L2 is
+    flushed before every timed step."""
+    import torch
+
+    import chunkwise_delta_rule_gb300 as kda
+    from chunkwise_delta_rule_gb300 import _lib
+    from workloads import make_case
+
+    dev = torch.device("cuda", 0)
+    cfg = DECODE
+    case = make_case(io="bf16", gate="channel", B=cfg["B"], T=1, H=cfg["H"], K=cfg["K"], V=cfg["V"],
+                     seed=7).to(dev)
+    state = case.h0.clone()
+    p = kda.make_problem(case.q, case.k, case.v, case.g, case.beta, gate="channel", scale=case.scale,
+                         initial_state=state)
+    lib = _lib.load()
+    l2 = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        kda.kda_recurrent_fwd(p, ht=state)
+    torch.cuda.synchronize()
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    clocks = ClockSampler()
+    clocks.start()
+    time.sleep(0.3)
+    profile_begin(lib)
+    for i in range(K):
+        l2.zero_()
+        ev[i][0].record()
+        kda.kda_recurrent_fwd(p, ht=state)
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    kern = profile_end(lib)
+    clk = clocks.stop()
+    ms = sum(a.elapsed_time(b) for a, b in ev) / K
+    B, H, D = cfg["B"], cfg["H"], cfg["K"]
+    by = B * H * (D * D * 4 * 2 + 2 * D * 2 + D * 4 + D * 2 + 2 + D * 2)   # state in/out; q, k; g; v; beta; o
+    n_l, tot = kern.get("k_recurrent", (K, ms * K))
+    avg = tot / max(n_l, 1)
+    pk = peaks()
+    ach = by / (avg * 1e-3) / 1e9
+    line = {"metric": "KDA decode tokens/s (token-by-token forward, in-place state), 1xGB300",
+            "value": round(B / (ms * 1e-3), 1), "unit": "tokens/s", "n_gpus": 1, "steps": K,
+            "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded)",
+            "config": {"workload": cfg["name"], "B": B, "T": 1, "H": H, "dk": D, "dv": D, "gate": "channel",
+                       "io": "bf16", "state": "fp32, updated in place",
+                       "l2": "flushed by a 256 MiB write before every timed step"},
+            "roofline": {"kernel": "k_recurrent", "bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm"],
+                         "unit": "GB/s", "frac": round(ach / pk["hbm"], 4), "traffic": None,
+                         "avg_launch_ms": round(avg, 5), "algorithmic_bytes": by,
+                         "peak_source": pk["source"] + " (MEASURED_PEAKS.json)"},
+            "gpu_launches": sum(v[0] for v in kern.values()), "clocks": clk}
+    print(json.dumps(line), flush=True)
+
+
 def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
@@ -531,6 +593,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--heads", type=int, default=0, help="restrict the workload to its first H heads (profiling)")
+    ap.add_argument("--decode", action="store_true",
+                    help="time the token-by-token forward on a decoding step instead of the headline")
     ap.add_argument("--policy", choices=["save", "recompute"], default="save",
                     help="save: the forward keeps its intermediates for the backward; recompute: the backward rebuilds them")
     args = ap.parse_args()
@@ -538,6 +602,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.decode:
+        run_decode(args)
     else:
         run_ours(args)
 

@@ -13,6 +13,7 @@ from .ops import (  # noqa: F401
     kda_chunk_fwd,
     kda_device_status,
     kda_last_error,
+    kda_recurrent_fwd,
     kda_saved_size,
     kda_workspace_size,
     make_problem,

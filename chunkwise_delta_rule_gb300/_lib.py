@@ -73,6 +73,8 @@ def load() -> ctypes.CDLL:
     lib.kda_device_status.restype = ctypes.c_int
     lib.kda_last_error.argtypes = []
     lib.kda_last_error.restype = ctypes.c_char_p
+    lib.kda_recurrent_fwd.argtypes = [P, vp, vp, vp, vp]
+    lib.kda_recurrent_fwd.restype = ctypes.c_int
     lib.kda_abi_version.argtypes = []
     lib.kda_abi_version.restype = ctypes.c_int
     _lib = lib

@@ -479,6 +479,23 @@ kda_status kda_chunk_bwd(const kda_problem* p, const void* dout, const float* dh
     return KDA_OK;
 }
 
+kda_status kda_recurrent_fwd(const kda_problem* p, void* o, float* ht, int32_t* err, kda_stream_t stream) {
+    Dims d;
+    kda_status st = check_dims(p, d);
+    if (st != KDA_OK) return st;
+    if ((st = check_inputs(p, d)) != KDA_OK) return st;
+    if (p->save_policy != 0) return fail(KDA_ERR_INVALID_ARG, "the recurrent forward has no saved buffer: use save_policy 0");
+    if (d.Ttot > 0 && !o) return fail(KDA_ERR_INVALID_ARG, "o must be non-NULL");
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    const kda::Shape s = shape_of(p, d);
+    cudaError_t e = traced("k_recurrent", cs, [&] {
+        return kda::launch_recurrent(s, p->io == KDA_BF16, (int)p->gate, p->T, p->cu_seqlens, p->q, p->k, p->v, p->beta,
+                                     p->g, p->h0, o, ht, err, cs);
+    });
+    if (e != cudaSuccess) return cuda_fail(e, "recurrent forward");
+    return KDA_OK;
+}
+
 int kda_profile_begin(void) {
     g_prof.on = true;
     g_prof.recs.clear();

@@ -188,6 +188,10 @@ void set_last_error(const char* msg);
 // --------------------------------------------------------------- launchers
 // Each returns cudaSuccess or the launch error. Defined in the .cu files.
 cudaError_t launch_table(const Shape& s, int B, int T, const int32_t* cu, Table t, cudaStream_t st);
+// token-by-token forward (kda_recurrent.cu); T = tokens per sequence when cu is NULL
+cudaError_t launch_recurrent(const Shape& s, int bf16, int gate, int T, const int32_t* cu, const void* q,
+                             const void* k, const void* v, const void* beta, const float* g, const float* h0,
+                             void* o, float* ht, int32_t* err, cudaStream_t st);
 
 cudaError_t launch_prep(const Shape& s, int io_bf16, int gate, const void* q, const void* k,
                         const void* v, const void* beta, const float* g, Table t, Fwd f,

@@ -1,0 +1,194 @@
+// Token-by-token forward of the gated delta rule, for decoding and short
+// prompts ("Kimi Delta Attention" derivation blog, §4 boxed KDA update):
+//     S~ = diag(exp g_t) S;  r_t = beta_t (v_t - S~^T k_t);  S = S~ + k_t r_t^T;  o_t = S^T (s q_t)
+// The update is separable over value columns (column v of S evolves with its
+// own entry of r_t), so a CTA owns a 32-column slice of one (sequence, head)
+// state and no two CTAs exchange anything. Warp w holds columns 8w..8w+7 of
+// the slice, lane l the keys l, l+32, ...; the slice stays in registers for
+// the whole call and is read and written once. Each token needs two sums over
+// keys (S~^T k and S^T q), formed by a butterfly that leaves every lane one
+// column's total. The next token's inputs are loaded while the current one is
+// processed.
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int RT = 128;   // 4 warps x 8 value columns
+constexpr int RV = 32;    // value columns per CTA
+constexpr unsigned FULL = 0xffffffffu;
+
+struct RecIO {
+    const void *q, *k, *v, *beta;
+    const float *g, *h0;
+    const int32_t* cu;
+    void* o;
+    float* ht;
+    int32_t* err;
+    int T;
+};
+
+// Column (of the warp's eight) whose total lane l holds after reduce8.
+__device__ __forceinline__ int rcol(int lane) { return ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1); }
+// A lane holding column c's total.
+__device__ __forceinline__ int rsrc(int c) { return ((c >> 2) & 1) * 16 + ((c >> 1) & 1) * 8 + (c & 1) * 4; }
+
+// Sums x[0..7] over the warp's 32 lanes (9 shuffles): each halving step keeps
+// half of the columns and adds the partner's copy of them.
+__device__ __forceinline__ float reduce8(const float (&x)[8], int lane) {
+    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+    float y[4], z[2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float send = b4 ? x[i] : x[i + 4];
+        y[i] = (b4 ? x[i + 4] : x[i]) + __shfl_xor_sync(FULL, send, 16);
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const float send = b3 ? y[i] : y[i + 2];
+        z[i] = (b3 ? y[i + 2] : y[i]) + __shfl_xor_sync(FULL, send, 8);
+    }
+    const float send = b2 ? z[0] : z[1];
+    float w = (b2 ? z[1] : z[0]) + __shfl_xor_sync(FULL, send, 4);
+    w += __shfl_xor_sync(FULL, w, 2);
+    w += __shfl_xor_sync(FULL, w, 1);
+    return w;
+}
+
+// Inputs of one token for this thread: its keys' k, s q and decay, its column's v, beta.
+template <typename TI, int KJ, int GATE>
+struct Tok {
+    float k[KJ], q[KJ], a[KJ], v, b;
+    __device__ __forceinline__ void load(const RecIO& io, size_t row, int H, int K, int V, int col, int lane,
+                                         float scale) {
+        const TI* kp = static_cast<const TI*>(io.k) + row * K + lane;
+        const TI* qp = static_cast<const TI*>(io.q) + row * K + lane;
+#pragma unroll
+        for (int j = 0; j < KJ; ++j) {
+            k[j] = ld(kp + 32 * j);
+            q[j] = scale * ld(qp + 32 * j);
+        }
+        if (GATE == 2) {
+#pragma unroll
+            for (int j = 0; j < KJ; ++j) a[j] = io.g[row * K + lane + 32 * j];
+        } else if (GATE == 1) {
+            const float gs = io.g[row];
+#pragma unroll
+            for (int j = 0; j < KJ; ++j) a[j] = gs;
+        }
+        v = ld(static_cast<const TI*>(io.v) + row * V + col);
+        b = ld(static_cast<const TI*>(io.beta) + row);
+        (void)H;
+    }
+};
+
+template <typename TI, int K, int GATE>
+__global__ void __launch_bounds__(RT) k_recurrent(Shape s, RecIO io) {
+    constexpr int KJ = K / 32;
+    const int VB = s.V / RV;
+    const int n = blockIdx.x / VB, vb = blockIdx.x - n * VB, h = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int H = s.H, V = s.V;
+    const int col0 = vb * RV + 8 * warp;   // first of this warp's eight columns
+    const int cme = col0 + rcol(lane);     // the column whose totals this lane holds
+    int t0, t1;
+    if (io.cu) {
+        t0 = io.cu[n];
+        t1 = io.cu[n + 1];
+        if (t0 < 0 || t1 < t0 || t1 > s.Ttot) {   // inconsistent offsets: an empty sequence
+            if (threadIdx.x == 0 && vb == 0 && h == 0 && io.err) atomicOr(io.err, 1);
+            t0 = t1 = 0;
+        }
+    } else {
+        t0 = n * io.T;
+        t1 = t0 + io.T;
+    }
+    // the state slice: keys lane + 32 j, columns col0 .. col0 + 7
+    float S[KJ][8];
+    const size_t sb = ((size_t)n * H + h) * K * V;
+#pragma unroll
+    for (int j = 0; j < KJ; ++j) {
+        if (io.h0) {
+            const float4* src = reinterpret_cast<const float4*>(io.h0 + sb + (size_t)(lane + 32 * j) * V + col0);
+            const float4 x0 = src[0], x1 = src[1];
+            S[j][0] = x0.x; S[j][1] = x0.y; S[j][2] = x0.z; S[j][3] = x0.w;
+            S[j][4] = x1.x; S[j][5] = x1.y; S[j][6] = x1.z; S[j][7] = x1.w;
+        } else {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) S[j][c] = 0.f;
+        }
+    }
+    Tok<TI, KJ, GATE> cur, nxt;
+    if (t0 < t1) cur.load(io, (size_t)t0 * H + h, H, K, V, cme, lane, s.scale);
+    for (int t = t0; t < t1; ++t) {
+        if (t + 1 < t1) nxt.load(io, (size_t)(t + 1) * H + h, H, K, V, cme, lane, s.scale);
+        // S~ = diag(alpha) S and p = S~^T k (this lane's keys)
+        float al[KJ];
+#pragma unroll
+        for (int j = 0; j < KJ; ++j) al[j] = (GATE == 0) ? 1.f : expf(cur.a[j]);
+        float p[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            float acc = 0.f;
+#pragma unroll
+            for (int j = 0; j < KJ; ++j) {
+                S[j][c] *= al[j];
+                acc = fmaf(S[j][c], cur.k[j], acc);
+            }
+            p[c] = acc;
+        }
+        const float rm = cur.b * (cur.v - reduce8(p, lane));   // r_t of column cme
+        // S = S~ + k r^T, then o = S^T (s q)
+        float oq[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const float r = __shfl_sync(FULL, rm, rsrc(c));
+            float acc = 0.f;
+#pragma unroll
+            for (int j = 0; j < KJ; ++j) {
+                S[j][c] = fmaf(cur.k[j], r, S[j][c]);
+                acc = fmaf(S[j][c], cur.q[j], acc);
+            }
+            oq[c] = acc;
+        }
+        const float ov = reduce8(oq, lane);
+        if ((lane & 3) == 0) st(static_cast<TI*>(io.o) + ((size_t)t * H + h) * V + cme, ov);
+        cur = nxt;
+    }
+    if (io.ht) {
+#pragma unroll
+        for (int j = 0; j < KJ; ++j) {
+            float4* dst = reinterpret_cast<float4*>(io.ht + sb + (size_t)(lane + 32 * j) * V + col0);
+            dst[0] = make_float4(S[j][0], S[j][1], S[j][2], S[j][3]);
+            dst[1] = make_float4(S[j][4], S[j][5], S[j][6], S[j][7]);
+        }
+    }
+}
+
+template <typename TI, int K>
+cudaError_t run_recurrent_k(const Shape& s, int gate, const RecIO& io, cudaStream_t st) {
+    const long long blocks = (long long)s.N * (s.V / RV);
+    if (blocks <= 0) return cudaSuccess;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+    const dim3 grid((unsigned)blocks, s.H);
+    switch (gate) {
+        case 0: k_recurrent<TI, K, 0><<<grid, RT, 0, st>>>(s, io); break;
+        case 1: k_recurrent<TI, K, 1><<<grid, RT, 0, st>>>(s, io); break;
+        default: k_recurrent<TI, K, 2><<<grid, RT, 0, st>>>(s, io); break;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_recurrent(const Shape& s, int bf16, int gate, int T, const int32_t* cu, const void* q,
+                             const void* k, const void* v, const void* beta, const float* g, const float* h0,
+                             void* o, float* ht, int32_t* err, cudaStream_t st) {
+    if (s.V % RV != 0 || (s.K != 64 && s.K != 128)) return cudaErrorInvalidValue;
+    RecIO io{q, k, v, beta, g, h0, cu, o, ht, err, T};
+    if (bf16) return s.K == 128 ? run_recurrent_k<__nv_bfloat16, 128>(s, gate, io, st)
+                                : run_recurrent_k<__nv_bfloat16, 64>(s, gate, io, st);
+    return s.K == 128 ? run_recurrent_k<float, 128>(s, gate, io, st) : run_recurrent_k<float, 64>(s, gate, io, st);
+}
+
+}  // namespace kda

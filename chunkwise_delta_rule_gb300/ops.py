@@ -142,6 +142,26 @@ def kda_chunk_fwd(p: Problem, *, output_final_state: bool = True, workspace=None
     return o, ht, sv
 
 
+def kda_recurrent_fwd(p: Problem, *, output_final_state: bool = True, ht: Optional[torch.Tensor] = None,
+                      err: Optional[torch.Tensor] = None, stream=None):
+    """Token-by-token forward (decoding, short prompts). Returns (o, ht or None).
+    ``ht`` may be given (fp32 [N, H, K, V], for example the initial state itself
+    for an in-place update); ``err`` is an optional int32 device word."""
+    _need(p.c.save_policy == 0, "the recurrent forward has no saved buffer: use save_policy 0")
+    dev = p.q.device
+    o = torch.empty_like(p.v)
+    if ht is None and output_final_state:
+        ht = torch.empty(p.state_shape, dtype=torch.float32, device=dev)
+    if ht is not None:
+        _need(ht.dtype == torch.float32 and ht.is_contiguous() and tuple(ht.shape) == p.state_shape,
+              "ht must be fp32 [N, H, K, V]")
+    if err is not None:
+        _need(err.dtype == torch.int32 and err.is_cuda and err.numel() >= 1, "err must be an int32 CUDA tensor")
+    st = _lib.load().kda_recurrent_fwd(ctypes.byref(p.c), _ptr(o), _ptr(ht), _ptr(err), _stream(stream))
+    _lib.check(st, "kda_recurrent_fwd")
+    return o, ht
+
+
 def kda_chunk_bwd(p: Problem, do: torch.Tensor, dht: Optional[torch.Tensor] = None, *,
                   saved=None, workspace=None, stream=None, need_dh0: bool = True):
     """Backward pass of <do, o> + <dht, ht>. Returns dq, dk, dv, dg, dbeta, dh0."""

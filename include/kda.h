@@ -137,6 +137,20 @@ kda_status kda_chunk_bwd(const kda_problem *p, const void *dout, const float *dh
 #define KDA_NOALLOC_SCRATCH_BYTES (32u << 20)
 kda_status kda_chunk_fwd_noalloc(const kda_problem *p, void *o, float *ht, kda_stream_t stream);
 
+/* Token-by-token forward for decoding and short prompts ("Kimi Delta
+ * Attention" derivation blog, §4 boxed KDA update; the fused recurrent form):
+ * the same problem description and tensors as kda_chunk_fwd, save_policy 0.
+ * Writes o [B*T, H, V] (io dtype; may be NULL when there are no tokens) and,
+ * if ht != NULL, the final states [N, H, K, V] fp32. Needs no workspace: each
+ * state is held on chip for the whole call and read and written once, so ht
+ * may be the same buffer as p->h0 (the state is updated in place). err is
+ * NULL or a device int32 word in which bit 0 is set (atomic OR) when
+ * cu_seqlens is inconsistent; such sequences are treated as empty. Any T is
+ * accepted, but the tokens of a (sequence, head) are processed one after the
+ * other: long prompts belong to kda_chunk_fwd. No backward counterpart.
+ * Enqueued on `stream`; returns after validation and launch. */
+kda_status kda_recurrent_fwd(const kda_problem *p, void *o, float *ht, int32_t *err, kda_stream_t stream);
+
 /* Synchronises `stream` and reads the device error word a previous call left
  * in `ws` (bit 0: cu_seqlens inconsistent and clamped; bit 1: a bounded wait
  * inside a kernel gave up, so that call's results are not valid). Returns

@@ -126,3 +126,18 @@ def test_missing_pointers_and_workspace():
     z = ctypes.c_void_p(0x3000)
     st = lib.kda_chunk_bwd(ctypes.byref(p), z, None, None, z, z, z, None, z, None, None, 0, None)
     assert st == 1 and "dg" in _lib.last_error()
+
+
+def test_recurrent_forward_validates_before_launch():
+    lib = _lib.load()
+    z = ctypes.c_void_p(0x3000)
+    p = _prob(save=1)
+    assert lib.kda_recurrent_fwd(ctypes.byref(p), z, None, None, None) == 1
+    assert "saved" in _lib.last_error()
+    p = _prob()
+    assert lib.kda_recurrent_fwd(ctypes.byref(p), None, None, None, None) == 1   # tokens but no o
+    p = _prob(K=96, V=96)
+    assert lib.kda_recurrent_fwd(ctypes.byref(p), z, None, None, None) == 2
+    p = _prob()
+    p.beta = None
+    assert lib.kda_recurrent_fwd(ctypes.byref(p), z, None, None, None) == 1
