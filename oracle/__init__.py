@@ -10,6 +10,9 @@ it, and it shares no code with the CUDA library.
   ReWY and seven-product backward, matrix intra, Gram elimination). It pins the
   equations the pages lost in extraction against the recurrence and is a
   debugging aid; it is never the reference a GPU result is graded against.
+* ``prologue`` -- numpy FP64 gate activation (softplus and lower-bound forms,
+  with A_log and dt_bias) and q/k L2 normalisation, forward and backward;
+  ``cases.run_oracle_prologue_arrays`` composes them with the recurrence.
 
 Parity pins: every function here is pinned by ``tests/test_oracle_*.py``
 against finite differences, closed forms, invariants and the pages' printed

@@ -93,3 +93,26 @@ def run_oracle_pairs(case, pairs, backward=True, nthreads=None):
         else:
             out[key] = [val[starts[i]:starts[i + 1], 0] for i in range(len(pairs))]
     return out
+
+
+def run_oracle_prologue_arrays(q, k, v, beta, g_raw, *, A_log, dt_bias, lower_bound, eps, scale, gate,
+                               seq_starts, h0=None, do=None, dht=None, backward=True, qk_norm=True,
+                               nthreads=None):
+    """The operator with its prologue on, as a composition: q, k normalised
+    per (token, head) (``qk_norm``), the decay activated from the raw gate
+    (``A_log`` not None), then the recurrence; with ``backward`` the
+    recurrence's gradients are carried back through the prologue
+    (``oracle.prologue``). Adds dA_log and ddt_bias (None without dt_bias)."""
+    from .prologue import gate_bwd, gate_fwd, l2norm_bwd, l2norm_fwd
+    qh = l2norm_fwd(q, eps)[0] if qk_norm else np.asarray(q, dtype=np.float64)
+    kh = l2norm_fwd(k, eps)[0] if qk_norm else np.asarray(k, dtype=np.float64)
+    g = g_raw if (A_log is None or g_raw is None) else gate_fwd(g_raw, A_log, dt_bias, lower_bound)
+    res = run_recurrence(qh, kh, v, beta, g, seq_starts, gate=gate, scale=scale, h0=h0, do=do, dht=dht,
+                         backward=backward, nthreads=nthreads)
+    if backward:
+        if qk_norm:
+            res["dq"] = l2norm_bwd(res["dq"], q, eps)
+            res["dk"] = l2norm_bwd(res["dk"], k, eps)
+        if A_log is not None and g_raw is not None:
+            res["dg"], res["dA_log"], res["ddt_bias"] = gate_bwd(res["dg"], g_raw, A_log, dt_bias, lower_bound)
+    return res
