@@ -261,12 +261,16 @@ def run_ours(args):
     case_cpu = make_config_case(args.config)
     if args.heads:
         case_cpu = heads_subset(case_cpu, args.heads)
+    pro = {}
+    if args.prologue:
+        case_cpu, pro = with_prologue(case_cpu)
+        pro = {k: v.to(dev) for k, v in pro.items()}
     case = case_cpu.to(dev)
     lib = _lib.load()
     save = 1 if args.policy == "save" else 0
     p = kda.make_problem(case.q, case.k, case.v, case.g, case.beta, gate=case.gate,
                          scale=case.scale, initial_state=case.h0, cu_seqlens=case.cu_seqlens,
-                         save_policy=save)
+                         save_policy=save, qk_l2norm=bool(args.prologue), **pro)
     wf = torch.empty(kda.kda_workspace_size(p, False), dtype=torch.uint8, device=dev)
     wb = torch.empty(kda.kda_workspace_size(p, True), dtype=torch.uint8, device=dev)
     sv = torch.empty(kda.kda_saved_size(p), dtype=torch.uint8, device=dev) if save else None
@@ -390,6 +394,8 @@ def run_ours(args):
             "config": {"workload": cfg["name"] + (f"_first{case.H}heads" if args.heads else ""), "B": case.B, "T": case.T, "H": case.H, "dk": case.K,
                        "dv": case.V, "gate": case.gate, "io": cfg["io"], "chunk": BT,
                        "policy": args.policy, "parallelism": f"replicas x{ws}",
+                       "prologue": ("raw gate activated in the operator (softplus form, A_log, dt_bias) and "
+                                    "q/k L2-normalised in the operator") if args.prologue else "off",
                        "l2": "flushed by a 256 MiB write before every timed step"},
             "tflops": round(tflops, 2), "tflops_executed": round(tflops_exec, 2),
             "frac_bf16_peak": round(tflops / pk["bf16"], 4),
@@ -486,6 +492,25 @@ def cpu_baseline(case_cpu):
     return {"value": round(v, 2), "unit": "tokens/s", "cores": cores, "kind": "oracle",
             "sample": f"{len(pairs)} whole (sequence, head) pairs = {th} token-heads, fp64 "
                       f"recurrence + BPTT, {dt:.1f} s wall; tokens/s = token-heads / H / wall"}
+
+
+def with_prologue(case):
+    """The workload with raw inputs for the in-operator prologue: q, k times a
+    per-(token, head) norm in [0.5, 3], a raw gate ~ N(0, 1), A_log = log U(1, 4)
+    per head and dt_bias = the softplus inverse of dt ~ logU(1e-3, 1e-1)."""
+    import math
+
+    import torch
+    gen = torch.Generator().manual_seed(12345)
+    B, T, H, K = case.q.shape
+    qn = torch.rand(B, T, H, 1, generator=gen) * 2.5 + 0.5
+    kn = torch.rand(B, T, H, 1, generator=gen) * 2.5 + 0.5
+    case.q = (case.q.float() * qn).to(case.q.dtype)
+    case.k = (case.k.float() * kn).to(case.k.dtype)
+    case.g = torch.randn(case.g.shape, generator=gen)
+    dt = torch.exp(torch.rand((H, K) if case.gate == "channel" else (H,), generator=gen)
+                   * (math.log(0.1) - math.log(1e-3)) + math.log(1e-3))
+    return case, dict(A_log=torch.log(torch.rand(H, generator=gen) * 3 + 1), dt_bias=dt + torch.log(-torch.expm1(-dt)))
 
 
 DECODE = dict(name="kda_decode_bf16", B=64, H=32, K=128, V=128)
@@ -593,6 +618,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--heads", type=int, default=0, help="restrict the workload to its first H heads (profiling)")
+    ap.add_argument("--prologue", action="store_true",
+                    help="raw gate and unnormalised q, k: activation and L2 norm inside the operator")
     ap.add_argument("--decode", action="store_true",
                     help="time the token-by-token forward on a decoding step instead of the headline")
     ap.add_argument("--policy", choices=["save", "recompute"], default="save",

@@ -37,6 +37,11 @@ class KdaProblem(ctypes.Structure):
         ("h0", ctypes.c_void_p),
         ("save_policy", ctypes.c_int),
         ("schedule", ctypes.c_int),
+        ("A_log", ctypes.c_void_p),
+        ("dt_bias", ctypes.c_void_p),
+        ("lower_bound", ctypes.c_float),
+        ("qk_l2norm", ctypes.c_int),
+        ("l2norm_eps", ctypes.c_float),
     ]
 
 
@@ -67,7 +72,7 @@ def load() -> ctypes.CDLL:
     lib.kda_saved_size.restype = sz
     lib.kda_chunk_fwd.argtypes = [P, vp, vp, vp, vp, sz, vp]
     lib.kda_chunk_fwd.restype = ctypes.c_int
-    lib.kda_chunk_bwd.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.kda_chunk_bwd.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.kda_chunk_bwd.restype = ctypes.c_int
     lib.kda_device_status.argtypes = [P, vp, sz, vp, ctypes.POINTER(ctypes.c_int32)]
     lib.kda_device_status.restype = ctypes.c_int

@@ -36,6 +36,11 @@ kda_status check_dims(const kda_problem* p, Dims& d) {
         return fail(KDA_ERR_INVALID_ARG, "unknown gate kind");
     if (p->save_policy != 0 && p->save_policy != 1)
         return fail(KDA_ERR_INVALID_ARG, "save_policy must be 0 or 1");
+    if (p->qk_l2norm != 0 && p->qk_l2norm != 1) return fail(KDA_ERR_INVALID_ARG, "qk_l2norm must be 0 or 1");
+    if (p->A_log && p->gate == KDA_GATE_NONE) return fail(KDA_ERR_INVALID_ARG, "A_log needs a gate");
+    if (p->dt_bias && !p->A_log) return fail(KDA_ERR_INVALID_ARG, "dt_bias needs A_log");
+    if (p->A_log && !(p->lower_bound == 0.f || (p->lower_bound >= -5.f && p->lower_bound < 0.f)))
+        return fail(KDA_ERR_INVALID_ARG, "lower_bound must be 0 or in [-5, 0)");
     const long long tok = (long long)p->B * p->T;
     if (tok > 0x7fffffffLL / 2) return fail(KDA_ERR_UNSUPPORTED, "too many tokens");
     d.Ttot = (int)tok;
@@ -180,6 +185,37 @@ kda::Shape shape_of(const kda_problem* p, const Dims& d) {
     return s;
 }
 
+// The optional prologue (normalised q, k; activated decay) and what it needs.
+bool has_prologue(const kda_problem* p) { return p->A_log || p->qk_l2norm; }
+float l2eps(const kda_problem* p) { return p->l2norm_eps > 0.f ? p->l2norm_eps : 1e-6f; }
+// The problem the chunk pipeline sees once the prologue has run.
+kda_problem core_problem(const kda_problem* p) {
+    kda_problem c = *p;
+    c.A_log = nullptr;
+    c.dt_bias = nullptr;
+    c.lower_bound = 0.f;
+    c.qk_l2norm = 0;
+    return c;
+}
+size_t gate_elems(const kda_problem* p, const Dims& d) {
+    return (size_t)d.Ttot * d.H * (p->gate == KDA_GATE_CHANNEL ? d.D : 1);
+}
+// Workspace after the pipeline's own: normalised q, k; activated decay; (backward) per-block partials.
+size_t prologue_bytes(const kda_problem* p, const Dims& d, bool bwd) {
+    if (!has_prologue(p) || d.Ttot == 0) return 0;
+    const size_t es = p->io == KDA_BF16 ? 2 : 4, tok = (size_t)d.Ttot * d.H * d.D;
+    size_t n = 0;
+    if (p->qk_l2norm) n += 2 * up(es * tok);
+    if (p->A_log) {
+        n += up(4 * gate_elems(p, d));
+        if (bwd) {
+            const size_t nb = (size_t)kda::prologue_blocks(d.Ttot);
+            n += up(4 * nb * d.H * (p->gate == KDA_GATE_CHANNEL ? d.D : 1)) + up(4 * nb * d.H);
+        }
+    }
+    return n;
+}
+
 kda_status check_inputs(const kda_problem* p, const Dims& d) {
     if (d.Ttot > 0 && (!p->q || !p->k || !p->v || !p->beta))
         return fail(KDA_ERR_INVALID_ARG, "q, k, v and beta must be non-NULL");
@@ -290,14 +326,11 @@ void set_last_error(const char* msg) { g_err = msg; }
 
 extern "C" {
 
-int kda_abi_version(void) { return 1; }
+int kda_abi_version(void) { return 2; }
 
 const char* kda_last_error(void) { return g_err.c_str(); }
 
-size_t kda_workspace_size(const kda_problem* p, int for_backward) {
-    Dims d;
-    if (check_dims(p, d) != KDA_OK) return 0;
-    if (d.Ttot == 0) return 0;
+static size_t core_workspace(const kda_problem* p, const Dims& d, int for_backward) {
     const Layout L = layout(d);
     if (use_tc(p)) {
         if (!for_backward) return L.table + (p->save_policy ? 0 : L.ftc);
@@ -305,6 +338,14 @@ size_t kda_workspace_size(const kda_problem* p, int for_backward) {
     }
     if (!for_backward) return L.table + (p->save_policy ? 0 : L.fcore);
     return L.table + (p->save_policy ? 0 : L.fcore + L.fextra) + L.bwd;
+}
+
+size_t kda_workspace_size(const kda_problem* p, int for_backward) {
+    Dims d;
+    if (check_dims(p, d) != KDA_OK) return 0;
+    if (d.Ttot == 0) return 0;
+    const kda_problem c = core_problem(p);
+    return core_workspace(&c, d, for_backward) + prologue_bytes(p, d, for_backward != 0);
 }
 
 size_t kda_saved_size(const kda_problem* p) {
@@ -315,8 +356,9 @@ size_t kda_saved_size(const kda_problem* p) {
     return use_tc(p) ? L.ftc + L.ftc_b : L.fcore + L.fextra;
 }
 
-kda_status kda_chunk_fwd(const kda_problem* p, void* o, float* ht, void* saved, void* ws,
-                         size_t ws_bytes, kda_stream_t stream) {
+// The chunk pipeline proper (the prologue, if any, has already run).
+static kda_status chunk_fwd_core(const kda_problem* p, void* o, float* ht, void* saved, void* ws,
+                                 size_t ws_bytes, kda_stream_t stream) {
     Dims d;
     kda_status st = check_dims(p, d);
     if (st != KDA_OK) return st;
@@ -380,9 +422,9 @@ kda_status kda_chunk_fwd(const kda_problem* p, void* o, float* ht, void* saved, 
     return KDA_OK;
 }
 
-kda_status kda_chunk_bwd(const kda_problem* p, const void* dout, const float* dht, const void* saved,
-                         void* dq, void* dk, void* dv, float* dg, void* dbeta, float* dh0, void* ws,
-                         size_t ws_bytes, kda_stream_t stream) {
+static kda_status chunk_bwd_core(const kda_problem* p, const void* dout, const float* dht, const void* saved,
+                                 void* dq, void* dk, void* dv, float* dg, void* dbeta, float* dh0, void* ws,
+                                 size_t ws_bytes, kda_stream_t stream) {
     Dims d;
     kda_status st = check_dims(p, d);
     if (st != KDA_OK) return st;
@@ -479,6 +521,110 @@ kda_status kda_chunk_bwd(const kda_problem* p, const void* dout, const float* dh
     return KDA_OK;
 }
 
+// Runs the prologue into the workspace past the pipeline's part (at `core` bytes) and
+// points a copy of the problem at its outputs.
+static kda_status run_prologue(const kda_problem* p, const Dims& d, char* w, kda_problem& c, cudaStream_t cs) {
+    Carver cv{w};
+    const size_t es = p->io == KDA_BF16 ? 2 : 4, tok = (size_t)d.Ttot * d.H * d.D;
+    kda::PrologueArgs a{};
+    a.q = p->q;
+    a.k = p->k;
+    a.g = p->g;
+    a.A_log = p->A_log;
+    a.dt_bias = p->dt_bias;
+    a.lower_bound = p->lower_bound;
+    a.eps = l2eps(p);
+    a.qk_norm = p->qk_l2norm;
+    if (p->qk_l2norm) {
+        a.qh = cv.take<char>(es * tok);
+        a.kh = cv.take<char>(es * tok);
+        c.q = a.qh;
+        c.k = a.kh;
+    }
+    if (p->A_log) {
+        a.ga = cv.take<float>(4 * gate_elems(p, d));
+        c.g = a.ga;
+    }
+    const kda::Shape s = shape_of(p, d);
+    cudaError_t e = traced("k_prologue", cs, [&] { return kda::launch_prologue(s, p->io == KDA_BF16, (int)p->gate, a, cs); });
+    return e == cudaSuccess ? KDA_OK : cuda_fail(e, "prologue");
+}
+
+kda_status kda_chunk_fwd(const kda_problem* p, void* o, float* ht, void* saved, void* ws, size_t ws_bytes,
+                         kda_stream_t stream) {
+    if (!p || !has_prologue(p)) return chunk_fwd_core(p, o, ht, saved, ws, ws_bytes, stream);
+    Dims d;
+    kda_status st = check_dims(p, d);
+    if (st != KDA_OK) return st;
+    if ((st = check_inputs(p, d)) != KDA_OK) return st;
+    kda_problem c = core_problem(p);
+    if (d.Ttot == 0) return chunk_fwd_core(&c, o, ht, saved, ws, ws_bytes, stream);
+    const size_t core = core_workspace(&c, d, 0);
+    if ((st = check_ws(ws, ws_bytes, core + prologue_bytes(p, d, false))) != KDA_OK) return st;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    if ((st = run_prologue(p, d, static_cast<char*>(ws) + core, c, cs)) != KDA_OK) return st;
+    return chunk_fwd_core(&c, o, ht, saved, ws, core, stream);
+}
+
+kda_status kda_chunk_bwd(const kda_problem* p, const void* dout, const float* dht, const void* saved, void* dq,
+                         void* dk, void* dv, float* dg, void* dbeta, float* dh0, float* dA_log, float* ddt_bias,
+                         void* ws, size_t ws_bytes, kda_stream_t stream) {
+    if (!p || !has_prologue(p))
+        return chunk_bwd_core(p, dout, dht, saved, dq, dk, dv, dg, dbeta, dh0, ws, ws_bytes, stream);
+    Dims d;
+    kda_status st = check_dims(p, d);
+    if (st != KDA_OK) return st;
+    if ((st = check_inputs(p, d)) != KDA_OK) return st;
+    kda_problem c = core_problem(p);
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    if (!p->A_log) dA_log = nullptr;
+    if (!p->dt_bias) ddt_bias = nullptr;
+    if (d.Ttot == 0) {   // no tokens: the parameters get zero gradients
+        cudaError_t e = cudaSuccess;
+        if (dA_log) e = cudaMemsetAsync(dA_log, 0, sizeof(float) * d.H, cs);
+        if (e == cudaSuccess && ddt_bias)
+            e = cudaMemsetAsync(ddt_bias, 0, sizeof(float) * d.H * (p->gate == KDA_GATE_CHANNEL ? d.D : 1), cs);
+        if (e != cudaSuccess) return cuda_fail(e, "zero parameter gradients");
+        return chunk_bwd_core(&c, dout, dht, saved, dq, dk, dv, dg, dbeta, dh0, ws, ws_bytes, stream);
+    }
+    const size_t core = core_workspace(&c, d, 1);
+    if ((st = check_ws(ws, ws_bytes, core + prologue_bytes(p, d, true))) != KDA_OK) return st;
+    char* w = static_cast<char*>(ws) + core;
+    if ((st = run_prologue(p, d, w, c, cs)) != KDA_OK) return st;
+    st = chunk_bwd_core(&c, dout, dht, saved, dq, dk, dv, dg, dbeta, dh0, ws, core, stream);
+    if (st != KDA_OK) return st;
+    // the prologue's buffers, then the partial sums
+    const size_t es = p->io == KDA_BF16 ? 2 : 4, tok = (size_t)d.Ttot * d.H * d.D;
+    Carver cv{w};
+    if (p->qk_l2norm) {
+        cv.take<char>(es * tok);
+        cv.take<char>(es * tok);
+    }
+    kda::EpilogueArgs a{};
+    a.q = p->q;
+    a.k = p->k;
+    a.g = p->g;
+    a.A_log = p->A_log;
+    a.dt_bias = p->dt_bias;
+    a.lower_bound = p->lower_bound;
+    a.eps = l2eps(p);
+    a.qk_norm = p->qk_l2norm;
+    a.dq = dq;
+    a.dk = dk;
+    a.dg = dg;
+    if (p->A_log) {
+        cv.take<float>(4 * gate_elems(p, d));
+        const size_t nb = (size_t)kda::prologue_blocks(d.Ttot);
+        a.pz = cv.take<float>(4 * nb * d.H * (p->gate == KDA_GATE_CHANNEL ? d.D : 1));
+        a.pA = cv.take<float>(4 * nb * d.H);
+    }
+    a.ddt_bias = ddt_bias;
+    a.dA_log = dA_log;
+    const kda::Shape s = shape_of(p, d);
+    cudaError_t e = traced("k_epilogue", cs, [&] { return kda::launch_epilogue(s, p->io == KDA_BF16, (int)p->gate, a, cs); });
+    return e == cudaSuccess ? KDA_OK : cuda_fail(e, "epilogue");
+}
+
 kda_status kda_recurrent_fwd(const kda_problem* p, void* o, float* ht, int32_t* err, kda_stream_t stream) {
     Dims d;
     kda_status st = check_dims(p, d);
@@ -490,7 +636,8 @@ kda_status kda_recurrent_fwd(const kda_problem* p, void* o, float* ht, int32_t* 
     const kda::Shape s = shape_of(p, d);
     cudaError_t e = traced("k_recurrent", cs, [&] {
         return kda::launch_recurrent(s, p->io == KDA_BF16, (int)p->gate, p->T, p->cu_seqlens, p->q, p->k, p->v, p->beta,
-                                     p->g, p->h0, o, ht, err, cs);
+                                     p->g, p->h0, o, ht, err, p->A_log, p->dt_bias, p->lower_bound, p->qk_l2norm,
+                                     l2eps(p), cs);
     });
     if (e != cudaSuccess) return cuda_fail(e, "recurrent forward");
     return KDA_OK;

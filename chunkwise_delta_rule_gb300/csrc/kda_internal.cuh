@@ -188,10 +188,33 @@ void set_last_error(const char* msg);
 // --------------------------------------------------------------- launchers
 // Each returns cudaSuccess or the launch error. Defined in the .cu files.
 cudaError_t launch_table(const Shape& s, int B, int T, const int32_t* cu, Table t, cudaStream_t st);
+// the optional input transforms (kda_prologue.cu): q, k normalised, decay activated
+struct PrologueArgs {
+    const void *q, *k;                      // raw q, k (io dtype)
+    const float *g, *A_log, *dt_bias;       // raw gate and its parameters (A_log NULL: no activation)
+    float lower_bound, eps;
+    int qk_norm;
+    void *qh, *kh;                          // normalised q, k (io dtype)
+    float* ga;                              // activated decay, shaped like g
+};
+struct EpilogueArgs {
+    const void *q, *k;
+    const float *g, *A_log, *dt_bias;
+    float lower_bound, eps;
+    int qk_norm;
+    void *dq, *dk;                          // in: gradients w.r.t. the normalised q, k; out: w.r.t. raw
+    float* dg;                              // in: w.r.t. the activated decay; out: w.r.t. the raw gate
+    float *pz, *pA;                         // per 64-token block partial sums [blocks][H][K or 1], [blocks][H]
+    float *ddt_bias, *dA_log;               // outputs (either may be NULL)
+};
+int prologue_blocks(int Ttot);
+cudaError_t launch_prologue(const Shape& s, int bf16, int gate, const PrologueArgs& a, cudaStream_t st);
+cudaError_t launch_epilogue(const Shape& s, int bf16, int gate, const EpilogueArgs& a, cudaStream_t st);
 // token-by-token forward (kda_recurrent.cu); T = tokens per sequence when cu is NULL
 cudaError_t launch_recurrent(const Shape& s, int bf16, int gate, int T, const int32_t* cu, const void* q,
                              const void* k, const void* v, const void* beta, const float* g, const float* h0,
-                             void* o, float* ht, int32_t* err, cudaStream_t st);
+                             void* o, float* ht, int32_t* err, const float* A_log, const float* dt_bias,
+                             float lower_bound, int qk_norm, float eps, cudaStream_t st);
 
 cudaError_t launch_prep(const Shape& s, int io_bf16, int gate, const void* q, const void* k,
                         const void* v, const void* beta, const float* g, Table t, Fwd f,

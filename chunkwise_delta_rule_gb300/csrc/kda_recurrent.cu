@@ -8,7 +8,11 @@
 // the whole call and is read and written once. Each token needs two sums over
 // keys (S~^T k and S^T q), formed by a butterfly that leaves every lane one
 // column's total. The next token's inputs are loaded while the current one is
-// processed.
+// processed. The optional prologue ("GatedDeltaNet-2 (NVlabs) — official spec
+// transcription", §3) runs per token on the loaded values: q and k divided by
+// sqrt(sum x^2 + eps) (every warp holds all keys, so a warp sum suffices), and
+// the decay -exp(A_log) softplus(g + dt_bias) or lower_bound sigmoid(exp(A_log)
+// (g + dt_bias)).
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -26,7 +30,20 @@ struct RecIO {
     float* ht;
     int32_t* err;
     int T;
+    const float *A_log, *dt_bias;   // prologue: A_log NULL = g is the decay itself
+    float lower_bound, eps;
+    int qk_norm;
 };
+
+__device__ __forceinline__ float rwsum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(FULL, x, o);
+    return x;
+}
+__device__ __forceinline__ float ract(float z, float eA, float lb) {
+    if (lb == 0.f) return -eA * (z > 20.f ? z : log1pf(expf(z)));
+    return lb / (1.f + expf(-eA * z));
+}
 
 // Column (of the warp's eight) whose total lane l holds after reduce8.
 __device__ __forceinline__ int rcol(int lane) { return ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1); }
@@ -55,30 +72,67 @@ __device__ __forceinline__ float reduce8(const float (&x)[8], int lane) {
     return w;
 }
 
-// Inputs of one token for this thread: its keys' k, s q and decay, its column's v, beta.
+// Inputs of one token for this thread: its keys' k, q and gate, its column's v,
+// beta. load() only issues the reads (the next token's are in flight while the
+// current one is processed); finish() applies the scale, the optional
+// normalisation and the gate activation, and turns the gate into the decay
+// factor exp(g).
 template <typename TI, int KJ, int GATE>
 struct Tok {
     float k[KJ], q[KJ], a[KJ], v, b;
-    __device__ __forceinline__ void load(const RecIO& io, size_t row, int H, int K, int V, int col, int lane,
-                                         float scale) {
+    __device__ __forceinline__ void load(const RecIO& io, size_t row, int K, int V, int col, int lane) {
         const TI* kp = static_cast<const TI*>(io.k) + row * K + lane;
         const TI* qp = static_cast<const TI*>(io.q) + row * K + lane;
 #pragma unroll
         for (int j = 0; j < KJ; ++j) {
             k[j] = ld(kp + 32 * j);
-            q[j] = scale * ld(qp + 32 * j);
+            q[j] = ld(qp + 32 * j);
         }
         if (GATE == 2) {
 #pragma unroll
             for (int j = 0; j < KJ; ++j) a[j] = io.g[row * K + lane + 32 * j];
         } else if (GATE == 1) {
-            const float gs = io.g[row];
-#pragma unroll
-            for (int j = 0; j < KJ; ++j) a[j] = gs;
+            a[0] = io.g[row];
         }
         v = ld(static_cast<const TI*>(io.v) + row * V + col);
         b = ld(static_cast<const TI*>(io.beta) + row);
-        (void)H;
+    }
+    __device__ __forceinline__ void finish(const RecIO& io, int h, int K, int lane, float scale) {
+        float sq = scale, sk = 1.f;
+        if (io.qk_norm) {
+            float ssq = 0.f, ssk = 0.f;
+#pragma unroll
+            for (int j = 0; j < KJ; ++j) {
+                ssq = fmaf(q[j], q[j], ssq);
+                ssk = fmaf(k[j], k[j], ssk);
+            }
+            sq = scale / sqrtf(rwsum(ssq) + io.eps);
+            sk = 1.f / sqrtf(rwsum(ssk) + io.eps);
+        }
+#pragma unroll
+        for (int j = 0; j < KJ; ++j) {
+            q[j] *= sq;
+            k[j] *= sk;
+        }
+        if (GATE == 1) {
+#pragma unroll
+            for (int j = 1; j < KJ; ++j) a[j] = a[0];
+        }
+        if (GATE != 0) {
+            const float eA = io.A_log ? expf(io.A_log[h]) : 0.f;
+#pragma unroll
+            for (int j = 0; j < KJ; ++j) {
+                float x = a[j];
+                if (io.A_log) {
+                    const float db = io.dt_bias ? (GATE == 2 ? io.dt_bias[h * K + lane + 32 * j] : io.dt_bias[h]) : 0.f;
+                    x = ract(x + db, eA, io.lower_bound);
+                }
+                a[j] = expf(x);
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < KJ; ++j) a[j] = 1.f;
+        }
     }
 };
 
@@ -119,13 +173,12 @@ __global__ void __launch_bounds__(RT) k_recurrent(Shape s, RecIO io) {
         }
     }
     Tok<TI, KJ, GATE> cur, nxt;
-    if (t0 < t1) cur.load(io, (size_t)t0 * H + h, H, K, V, cme, lane, s.scale);
+    if (t0 < t1) cur.load(io, (size_t)t0 * H + h, K, V, cme, lane);
     for (int t = t0; t < t1; ++t) {
-        if (t + 1 < t1) nxt.load(io, (size_t)(t + 1) * H + h, H, K, V, cme, lane, s.scale);
+        if (t + 1 < t1) nxt.load(io, (size_t)(t + 1) * H + h, K, V, cme, lane);
+        cur.finish(io, h, K, lane, s.scale);
         // S~ = diag(alpha) S and p = S~^T k (this lane's keys)
-        float al[KJ];
-#pragma unroll
-        for (int j = 0; j < KJ; ++j) al[j] = (GATE == 0) ? 1.f : expf(cur.a[j]);
+        const float (&al)[KJ] = cur.a;
         float p[8];
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
@@ -183,9 +236,10 @@ cudaError_t run_recurrent_k(const Shape& s, int gate, const RecIO& io, cudaStrea
 
 cudaError_t launch_recurrent(const Shape& s, int bf16, int gate, int T, const int32_t* cu, const void* q,
                              const void* k, const void* v, const void* beta, const float* g, const float* h0,
-                             void* o, float* ht, int32_t* err, cudaStream_t st) {
+                             void* o, float* ht, int32_t* err, const float* A_log, const float* dt_bias,
+                             float lower_bound, int qk_norm, float eps, cudaStream_t st) {
     if (s.V % RV != 0 || (s.K != 64 && s.K != 128)) return cudaErrorInvalidValue;
-    RecIO io{q, k, v, beta, g, h0, cu, o, ht, err, T};
+    RecIO io{q, k, v, beta, g, h0, cu, o, ht, err, T, A_log, dt_bias, lower_bound, eps, qk_norm};
     if (bf16) return s.K == 128 ? run_recurrent_k<__nv_bfloat16, 128>(s, gate, io, st)
                                 : run_recurrent_k<__nv_bfloat16, 64>(s, gate, io, st);
     return s.K == 128 ? run_recurrent_k<float, 128>(s, gate, io, st) : run_recurrent_k<float, 64>(s, gate, io, st);

@@ -41,6 +41,8 @@ class Problem:
     h0: Optional[torch.Tensor]
     cu_seqlens: Optional[torch.Tensor]
     N: int
+    A_log: Optional[torch.Tensor] = None
+    dt_bias: Optional[torch.Tensor] = None
 
     @property
     def state_shape(self):
@@ -54,7 +56,14 @@ def _need(cond: bool, msg: str):
 
 def make_problem(q, k, v, g, beta, *, gate: str, scale: Optional[float] = None,
                  initial_state: Optional[torch.Tensor] = None,
-                 cu_seqlens: Optional[torch.Tensor] = None, save_policy: int = 0) -> Problem:
+                 cu_seqlens: Optional[torch.Tensor] = None, save_policy: int = 0,
+                 A_log: Optional[torch.Tensor] = None, dt_bias: Optional[torch.Tensor] = None,
+                 lower_bound: float = 0.0, qk_l2norm: bool = False, l2norm_eps: float = 1e-6) -> Problem:
+    """Describe one call. With ``A_log`` (fp32 [H]) ``g`` is the raw gate and the
+    decay is activated inside the operator (softplus form, or the lower-bound
+    form when ``lower_bound`` < 0), with the optional ``dt_bias`` (fp32, [H, K]
+    for a per-channel gate, [H] for a scalar one); ``qk_l2norm`` normalises q
+    and k per (token, head) first."""
     _need(q.dim() == 4 and k.shape == q.shape, "q and k must be [B, T, H, K]")
     B, T, H, K = q.shape
     _need(v.dim() == 4 and v.shape[:3] == q.shape[:3], "v must be [B, T, H, V]")
@@ -91,7 +100,21 @@ def make_problem(q, k, v, g, beta, *, gate: str, scale: Optional[float] = None,
     c.h0 = None if initial_state is None else initial_state.data_ptr()
     c.save_policy = int(save_policy)
     c.schedule = 0
-    return Problem(c, q, k, v, beta, g, initial_state, cu_seqlens, N)
+    if A_log is not None:
+        _need(gate != "none", "A_log needs a gate")
+        _need(A_log.dtype == torch.float32 and A_log.is_cuda and A_log.is_contiguous()
+              and tuple(A_log.shape) == (H,), "A_log must be a contiguous fp32 CUDA tensor [H]")
+    if dt_bias is not None:
+        _need(A_log is not None, "dt_bias needs A_log")
+        want = (H, K) if gate == "channel" else (H,)
+        _need(dt_bias.dtype == torch.float32 and dt_bias.is_cuda and dt_bias.is_contiguous()
+              and tuple(dt_bias.shape) == want, f"dt_bias must be a contiguous fp32 CUDA tensor {list(want)}")
+    c.A_log = None if A_log is None else A_log.data_ptr()
+    c.dt_bias = None if dt_bias is None else dt_bias.data_ptr()
+    c.lower_bound = float(lower_bound)
+    c.qk_l2norm = 1 if qk_l2norm else 0
+    c.l2norm_eps = float(l2norm_eps)
+    return Problem(c, q, k, v, beta, g, initial_state, cu_seqlens, N, A_log, dt_bias)
 
 
 def kda_workspace_size(p: Problem, for_backward: bool) -> int:
@@ -164,7 +187,9 @@ def kda_recurrent_fwd(p: Problem, *, output_final_state: bool = True, ht: Option
 
 def kda_chunk_bwd(p: Problem, do: torch.Tensor, dht: Optional[torch.Tensor] = None, *,
                   saved=None, workspace=None, stream=None, need_dh0: bool = True):
-    """Backward pass of <do, o> + <dht, ht>. Returns dq, dk, dv, dg, dbeta, dh0."""
+    """Backward pass of <do, o> + <dht, ht>. Returns dq, dk, dv, dg, dbeta, dh0,
+    and, when the problem activates its gate (A_log given), also dA_log and
+    ddt_bias (None without dt_bias)."""
     lib = _lib.load()
     dev = p.q.device
     _need(do.shape == p.v.shape and do.dtype == p.v.dtype and do.is_contiguous(), "do must match v")
@@ -177,12 +202,16 @@ def kda_chunk_bwd(p: Problem, do: torch.Tensor, dht: Optional[torch.Tensor] = No
     dbeta = torch.empty_like(p.beta)
     dg = None if p.g is None else torch.empty_like(p.g)
     dh0 = torch.empty(p.state_shape, dtype=torch.float32, device=dev) if need_dh0 else None
+    dA = None if p.A_log is None else torch.empty_like(p.A_log)
+    ddt = None if p.dt_bias is None else torch.empty_like(p.dt_bias)
     ws = _buffer(kda_workspace_size(p, True), dev, workspace)
     nbytes = 0 if ws is None else ws.numel() * ws.element_size()
     st = lib.kda_chunk_bwd(ctypes.byref(p.c), _ptr(do), _ptr(dht), _ptr(saved), _ptr(dq), _ptr(dk),
-                           _ptr(dv), _ptr(dg), _ptr(dbeta), _ptr(dh0), _ptr(ws), nbytes,
+                           _ptr(dv), _ptr(dg), _ptr(dbeta), _ptr(dh0), _ptr(dA), _ptr(ddt), _ptr(ws), nbytes,
                            _stream(stream))
     _lib.check(st, "kda_chunk_bwd")
+    if p.A_log is not None:
+        return dq, dk, dv, dg, dbeta, dh0, dA, ddt
     return dq, dk, dv, dg, dbeta, dh0
 
 
@@ -190,35 +219,44 @@ class ChunkKDAFunction(torch.autograd.Function):
     """Autograd wrapper: forward and backward both run the CUDA library."""
 
     @staticmethod
-    def forward(ctx, q, k, v, g, beta, initial_state, gate, scale, cu_seqlens, save_policy):
-        p = make_problem(q, k, v, g, beta, gate=gate, scale=scale, initial_state=initial_state,
-                         cu_seqlens=cu_seqlens, save_policy=save_policy)
+    def forward(ctx, q, k, v, g, beta, initial_state, A_log, dt_bias, gate, scale, cu_seqlens, save_policy,
+                lower_bound, qk_l2norm, l2norm_eps):
+        kw = dict(gate=gate, scale=scale, save_policy=save_policy, lower_bound=lower_bound,
+                  qk_l2norm=qk_l2norm, l2norm_eps=l2norm_eps)
+        p = make_problem(q, k, v, g, beta, initial_state=initial_state, cu_seqlens=cu_seqlens,
+                         A_log=A_log, dt_bias=dt_bias, **kw)
         o, ht, sv = kda_chunk_fwd(p)
-        ctx.save_for_backward(q, k, v, g if g is not None else torch.empty(0), beta,
-                              initial_state if initial_state is not None else torch.empty(0),
-                              cu_seqlens if cu_seqlens is not None else torch.empty(0),
-                              sv if sv is not None else torch.empty(0))
-        ctx.meta = (gate, scale, g is not None, initial_state is not None, cu_seqlens is not None,
-                    save_policy)
+        e = torch.empty(0)
+        ctx.save_for_backward(q, k, v, g if g is not None else e, beta,
+                              initial_state if initial_state is not None else e,
+                              cu_seqlens if cu_seqlens is not None else e, sv if sv is not None else e,
+                              A_log if A_log is not None else e, dt_bias if dt_bias is not None else e)
+        ctx.meta = (kw, g is not None, initial_state is not None, cu_seqlens is not None, A_log is not None,
+                    dt_bias is not None)
         return o, ht
 
     @staticmethod
     def backward(ctx, do, dht):
-        q, k, v, g, beta, h0, cu, sv = ctx.saved_tensors
-        gate, scale, has_g, has_h0, has_cu, save_policy = ctx.meta
-        p = make_problem(q, k, v, g if has_g else None, beta, gate=gate, scale=scale,
-                         initial_state=h0 if has_h0 else None, cu_seqlens=cu if has_cu else None,
-                         save_policy=save_policy)
+        q, k, v, g, beta, h0, cu, sv, A_log, dt_bias = ctx.saved_tensors
+        kw, has_g, has_h0, has_cu, has_A, has_dt = ctx.meta
+        p = make_problem(q, k, v, g if has_g else None, beta, initial_state=h0 if has_h0 else None,
+                         cu_seqlens=cu if has_cu else None, A_log=A_log if has_A else None,
+                         dt_bias=dt_bias if has_dt else None, **kw)
         do = do.contiguous()
         dht = None if dht is None else dht.contiguous()
-        dq, dk, dv, dg, dbeta, dh0 = kda_chunk_bwd(p, do, dht, saved=sv if save_policy else None,
-                                                   need_dh0=has_h0)
-        return dq, dk, dv, dg, dbeta, dh0, None, None, None, None
+        r = kda_chunk_bwd(p, do, dht, saved=sv if kw["save_policy"] else None, need_dh0=has_h0)
+        dq, dk, dv, dg, dbeta, dh0 = r[:6]
+        dA, ddt = (r[6], r[7]) if has_A else (None, None)
+        return dq, dk, dv, dg, dbeta, dh0, dA, ddt, None, None, None, None, None, None, None
 
 
 def chunk_kda(q, k, v, g, beta, *, gate: str = "channel", scale: Optional[float] = None,
               initial_state: Optional[torch.Tensor] = None,
-              cu_seqlens: Optional[torch.Tensor] = None, save_policy: int = 0):
-    """Differentiable chunkwise gated delta rule. Returns (o, final_state)."""
-    return ChunkKDAFunction.apply(q, k, v, g, beta, initial_state, gate, scale, cu_seqlens,
-                                  save_policy)
+              cu_seqlens: Optional[torch.Tensor] = None, save_policy: int = 0,
+              A_log: Optional[torch.Tensor] = None, dt_bias: Optional[torch.Tensor] = None,
+              lower_bound: float = 0.0, use_qk_l2norm_in_kernel: bool = False, l2norm_eps: float = 1e-6):
+    """Differentiable chunkwise gated delta rule. Returns (o, final_state).
+    With ``A_log`` the gate ``g`` is raw and activated inside the operator;
+    ``use_qk_l2norm_in_kernel`` normalises q and k per (token, head)."""
+    return ChunkKDAFunction.apply(q, k, v, g, beta, initial_state, A_log, dt_bias, gate, scale, cu_seqlens,
+                                  save_policy, lower_bound, use_qk_l2norm_in_kernel, l2norm_eps)

@@ -82,6 +82,17 @@ typedef struct {
     int save_policy;            /* 0: backward recomputes the forward (policy R);
                                    1: forward fills `saved` for the backward (policy A) */
     int schedule;               /* 0: default; reserved for producer/consumer schedules */
+    /* Optional prologue inside the operator ("GatedDeltaNet-2 (NVlabs) — official spec
+     * transcription", §2.0, §3, §4.2); all zero / NULL turns it off. */
+    const float *A_log;         /* [H] fp32 or NULL. Non-NULL (needs a gate): g holds the raw gate and
+                                   the decay is -exp(A_log) softplus(g + dt_bias) when lower_bound
+                                   == 0, else lower_bound sigmoid(exp(A_log) (g + dt_bias)); the
+                                   activated decay must meet the bound on g above */
+    const float *dt_bias;       /* NULL or fp32 [H, K] (CHANNEL) / [H] (SCALAR); needs A_log */
+    float lower_bound;          /* 0 (softplus form) or in [-5, 0) (lower-bound form) */
+    int qk_l2norm;              /* 1: q and k are L2-normalised per (token, head) first:
+                                   x / sqrt(sum x^2 + l2norm_eps) */
+    float l2norm_eps;           /* <= 0 selects 1e-6 */
 } kda_problem;
 
 /* Bytes of device workspace kda_chunk_fwd (for_backward = 0) or kda_chunk_bwd
@@ -107,11 +118,16 @@ kda_status kda_chunk_fwd(const kda_problem *p, void *o, float *ht, void *saved, 
  * what kda_chunk_fwd wrote for the same inputs. Outputs: dq, dk [B*T, H, K],
  * dv [B*T, H, V], dbeta [B*T, H] (io dtype); dg fp32 shaped like g (NULL iff
  * gate == NONE); dh0 [N, H, K, V] fp32 (may be NULL). dq is the gradient with
- * respect to the unscaled q; dg is with respect to the natural-log decay. */
+ * respect to the unscaled q; dg is with respect to the natural-log decay.
+ * With the prologue on, dq, dk and dg are with respect to the raw inputs, and
+ * dA_log [H] and ddt_bias (shaped like dt_bias) receive the parameters'
+ * gradients (each may be NULL; ignored when its parameter is absent). The
+ * parameter gradients are sums over tokens formed in a fixed order (no
+ * atomics), so repeated calls agree bitwise. */
 kda_status kda_chunk_bwd(const kda_problem *p, const void *dout, const float *dht,
                          const void *saved, void *dq, void *dk, void *dv, float *dg,
-                         void *dbeta, float *dh0, void *ws, size_t ws_bytes,
-                         kda_stream_t stream);
+                         void *dbeta, float *dh0, float *dA_log, float *ddt_bias, void *ws,
+                         size_t ws_bytes, kda_stream_t stream);
 
 /* Forward pass for callers that cannot allocate device memory: code running
  * inside an allocator's own hooks, processes whose device memory is fully

@@ -24,7 +24,7 @@ def test_library_exports_every_declared_symbol():
     assert "kda_chunk_fwd" in names and "kda_chunk_bwd" in names
     for n in names:
         assert hasattr(lib, n), n
-    assert lib.kda_abi_version() == 1
+    assert lib.kda_abi_version() == 2
 
 
 def _prob(**kw):
@@ -124,7 +124,7 @@ def test_missing_pointers_and_workspace():
                              ctypes.c_void_p(0x10000), 100, None) == 3
     # backward: dg required with a gate
     z = ctypes.c_void_p(0x3000)
-    st = lib.kda_chunk_bwd(ctypes.byref(p), z, None, None, z, z, z, None, z, None, None, 0, None)
+    st = lib.kda_chunk_bwd(ctypes.byref(p), z, None, None, z, z, z, None, z, None, None, None, None, 0, None)
     assert st == 1 and "dg" in _lib.last_error()
 
 
@@ -141,3 +141,32 @@ def test_recurrent_forward_validates_before_launch():
     p = _prob()
     p.beta = None
     assert lib.kda_recurrent_fwd(ctypes.byref(p), z, None, None, None) == 1
+
+
+def test_prologue_fields_are_validated_and_sized():
+    lib = _lib.load()
+    z = ctypes.c_void_p(0x3000)
+    base = _prob()
+    core_f, core_b = _ws(base, 0), _ws(base, 1)
+    # A_log without a gate, dt_bias without A_log, lower_bound out of range, qk_l2norm not 0/1
+    for kw, fld in ((dict(gate=0), ("A_log", 0x5000)), (dict(), ("dt_bias", 0x5000)), (dict(), ("qk_l2norm", 2))):
+        p = _prob(**kw)
+        setattr(p, *fld)
+        assert lib.kda_chunk_fwd(ctypes.byref(p), z, None, None, None, 0, None) == 1
+        assert _ws(p, 0) == 0
+    p = _prob()
+    p.A_log = 0x5000
+    p.lower_bound = -6.0
+    assert lib.kda_chunk_fwd(ctypes.byref(p), z, None, None, None, 0, None) == 1
+    def up(x):
+        return (x + 255) // 256 * 256
+
+    # workspace: the pipeline's, then normalised q, k (io dtype), the activated gate and,
+    # in the backward, per-64-token-block partial sums
+    p = _prob()   # bf16, channel gate, B=2, T=130, H=3, K=128
+    p.A_log, p.dt_bias, p.qk_l2norm = 0x5000, 0x6000, 1
+    tok = 2 * 130 * 3 * 128
+    nb = (2 * 130 + 63) // 64
+    extra_f = 2 * up(2 * tok) + up(4 * tok)
+    assert _ws(p, 0) == core_f + extra_f
+    assert _ws(p, 1) == core_b + extra_f + up(4 * nb * 3 * 128) + up(4 * nb * 3)
