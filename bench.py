@@ -379,10 +379,10 @@ def run_ours(args):
         kernels[k] = rec
 
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not args.prologue:   # (the end-to-end and CPU legs time the headline problem)
         e2e = run_e2e(args, case_cpu, dev, kda, K)
     cpu = None
-    if rank == 0 and ws == 1 and not args.no_cpu:
+    if rank == 0 and ws == 1 and not args.no_cpu and not args.prologue:
         cpu = cpu_baseline(case_cpu)
 
     if rank == 0:
