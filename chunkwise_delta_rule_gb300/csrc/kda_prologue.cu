@@ -45,106 +45,167 @@ __device__ __forceinline__ void act_grad(float z, float eA, float lb, float& dz,
     }
 }
 
-// x_hat = x r of one (token, head) row, r = (sum x^2 + eps)^(-1/2); lane holds x[lane + 32 j]
-template <int KJ>
-__device__ __forceinline__ float row_rnorm(const float (&x)[KJ], float eps) {
+// A lane's EL consecutive elements of a row (one vector access).
+__device__ __forceinline__ void ldv(const float* p, float (&x)[4]) {
+    const float4 v = *reinterpret_cast<const float4*>(p);
+    x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+}
+__device__ __forceinline__ void ldv(const float* p, float (&x)[2]) {
+    const float2 v = *reinterpret_cast<const float2*>(p);
+    x[0] = v.x; x[1] = v.y;
+}
+__device__ __forceinline__ void ldv(const __nv_bfloat16* p, float (&x)[4]) {
+    const uint2 v = *reinterpret_cast<const uint2*>(p);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+    const float2 a = __bfloat1622float2(h[0]), b = __bfloat1622float2(h[1]);
+    x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
+}
+__device__ __forceinline__ void ldv(const __nv_bfloat16* p, float (&x)[2]) {
+    const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(p);
+    const float2 a = __bfloat1622float2(v);
+    x[0] = a.x; x[1] = a.y;
+}
+__device__ __forceinline__ void stv(float* p, const float (&x)[4]) { *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]); }
+__device__ __forceinline__ void stv(float* p, const float (&x)[2]) { *reinterpret_cast<float2*>(p) = make_float2(x[0], x[1]); }
+__device__ __forceinline__ void stv(__nv_bfloat16* p, const float (&x)[4]) {
+    uint2 v;
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&v);
+    h[0] = __floats2bfloat162_rn(x[0], x[1]);
+    h[1] = __floats2bfloat162_rn(x[2], x[3]);
+    *reinterpret_cast<uint2*>(p) = v;
+}
+__device__ __forceinline__ void stv(__nv_bfloat16* p, const float (&x)[2]) {
+    *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(x[0], x[1]);
+}
+
+// r = (sum x^2 + eps)^(-1/2) of one (token, head) row spread over the warp
+template <int EL>
+__device__ __forceinline__ float row_rnorm(const float (&x)[EL], float eps) {
     float ss = 0.f;
 #pragma unroll
-    for (int j = 0; j < KJ; ++j) ss = fmaf(x[j], x[j], ss);
+    for (int e = 0; e < EL; ++e) ss = fmaf(x[e], x[e], ss);
     return 1.f / sqrtf(warp_sum(ss) + eps);
 }
 
+// One warp per (token, head) row; lane l owns elements EL l .. EL l + EL - 1.
 template <typename TI, int K, int GATE>
 __global__ void __launch_bounds__(32 * PW) k_prologue(int rows, int H, PrologueArgs a) {
-    constexpr int KJ = K / 32;
+    constexpr int EL = K / 32;
     const int row = blockIdx.x * PW + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (row >= rows) return;
-    const int h = row % H;
+    const int h = row % H, c0 = EL * lane;
+    float xq[EL], xk[EL], z[EL], db[EL];
     if (a.qk_norm) {
-#pragma unroll
-        for (int w = 0; w < 2; ++w) {
-            const TI* src = static_cast<const TI*>(w ? a.k : a.q) + (size_t)row * K + lane;
-            TI* dst = static_cast<TI*>(w ? a.kh : a.qh) + (size_t)row * K + lane;
-            float x[KJ];
-#pragma unroll
-            for (int j = 0; j < KJ; ++j) x[j] = ld(src + 32 * j);
-            const float r = row_rnorm<KJ>(x, a.eps);
-#pragma unroll
-            for (int j = 0; j < KJ; ++j) st(dst + 32 * j, x[j] * r);
-        }
+        ldv(static_cast<const TI*>(a.q) + (size_t)row * K + c0, xq);
+        ldv(static_cast<const TI*>(a.k) + (size_t)row * K + c0, xk);
     }
-    if (GATE != 0 && a.A_log) {
+    const bool act_on = GATE != 0 && a.A_log;
+    if (act_on && GATE == 2) {
+        ldv(a.g + (size_t)row * K + c0, z);
+        if (a.dt_bias) ldv(a.dt_bias + (size_t)h * K + c0, db);
+    }
+    if (a.qk_norm) {
+        const float rq = row_rnorm<EL>(xq, a.eps), rk = row_rnorm<EL>(xk, a.eps);
+#pragma unroll
+        for (int e = 0; e < EL; ++e) {
+            xq[e] *= rq;
+            xk[e] *= rk;
+        }
+        stv(static_cast<TI*>(a.qh) + (size_t)row * K + c0, xq);
+        stv(static_cast<TI*>(a.kh) + (size_t)row * K + c0, xk);
+    }
+    if (act_on) {
         const float eA = expf(a.A_log[h]);
         if (GATE == 2) {
 #pragma unroll
-            for (int j = 0; j < KJ; ++j) {
-                const int c = lane + 32 * j;
-                const float z = a.g[(size_t)row * K + c] + (a.dt_bias ? a.dt_bias[h * K + c] : 0.f);
-                a.ga[(size_t)row * K + c] = act(z, eA, a.lower_bound);
-            }
+            for (int e = 0; e < EL; ++e) z[e] = act(z[e] + (a.dt_bias ? db[e] : 0.f), eA, a.lower_bound);
+            stv(a.ga + (size_t)row * K + c0, z);
         } else if (lane == 0) {
-            const float z = a.g[row] + (a.dt_bias ? a.dt_bias[h] : 0.f);
-            a.ga[row] = act(z, eA, a.lower_bound);
+            a.ga[row] = act(a.g[row] + (a.dt_bias ? a.dt_bias[h] : 0.f), eA, a.lower_bound);
         }
     }
 }
 
+// One CTA per (64-token block, head); warp w takes tokens w, w + 8, ... of the block, two at a
+// time (both tokens' loads in flight before either reduction).
 template <typename TI, int K, int GATE>
 __global__ void __launch_bounds__(32 * PW) k_epilogue(int Ttot, int H, EpilogueArgs a) {
-    constexpr int KJ = K / 32;
+    constexpr int EL = K / 32;
     __shared__ float sZ[PW][K];
     __shared__ float sAp[PW];
     const int tb = blockIdx.x, h = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c0 = EL * lane;
     const bool gated = GATE != 0 && a.A_log;
     const float eA = gated ? expf(a.A_log[h]) : 0.f;
-    float accz[KJ], accA = 0.f;
+    float db[EL];
 #pragma unroll
-    for (int j = 0; j < KJ; ++j) accz[j] = 0.f;
-    for (int t = tb * ETB + warp; t < min(Ttot, tb * ETB + ETB); t += PW) {
-        const size_t row = (size_t)t * H + h;
-        if (a.qk_norm) {
+    for (int e = 0; e < EL; ++e) db[e] = 0.f;
+    if (gated && a.dt_bias) {
+        if (GATE == 2) ldv(a.dt_bias + (size_t)h * K + c0, db);
+        else db[0] = a.dt_bias[h];
+    }
+    float accz[EL], accA = 0.f;
 #pragma unroll
-            for (int w = 0; w < 2; ++w) {
-                const TI* xs = static_cast<const TI*>(w ? a.k : a.q) + row * K + lane;
-                TI* dx = static_cast<TI*>(w ? a.dk : a.dq) + row * K + lane;
-                float x[KJ], d[KJ];
+    for (int e = 0; e < EL; ++e) accz[e] = 0.f;
+    const int tend = min(Ttot, tb * ETB + ETB);
+    for (int t0 = tb * ETB + warp; t0 < tend; t0 += 2 * PW) {
+        float xq[2][EL], dq[2][EL], xk[2][EL], dk[2][EL], zg[2][EL], ug[2][EL];
+        bool in[2];
 #pragma unroll
-                for (int j = 0; j < KJ; ++j) {
-                    x[j] = ld(xs + 32 * j);
-                    d[j] = ld(dx + 32 * j);
+        for (int u = 0; u < 2; ++u) {
+            const int t = t0 + u * PW;
+            in[u] = t < tend;
+            if (!in[u]) continue;
+            const size_t row = (size_t)t * H + h;
+            if (a.qk_norm) {
+                ldv(static_cast<const TI*>(a.q) + row * K + c0, xq[u]);
+                ldv(static_cast<const TI*>(a.dq) + row * K + c0, dq[u]);
+                ldv(static_cast<const TI*>(a.k) + row * K + c0, xk[u]);
+                ldv(static_cast<const TI*>(a.dk) + row * K + c0, dk[u]);
+            }
+            if (gated) {
+                if (GATE == 2) {
+                    ldv(a.g + row * K + c0, zg[u]);
+                    ldv(a.dg + row * K + c0, ug[u]);
+                } else if (lane == 0) {
+                    zg[u][0] = a.g[row];
+                    ug[u][0] = a.dg[row];
                 }
-                const float r = row_rnorm<KJ>(x, a.eps);
-                float dot = 0.f;
-#pragma unroll
-                for (int j = 0; j < KJ; ++j) dot = fmaf(x[j] * r, d[j], dot);
-                dot = warp_sum(dot);
-#pragma unroll
-                for (int j = 0; j < KJ; ++j) st(dx + 32 * j, r * (d[j] - x[j] * r * dot));
             }
         }
-        if (gated) {
-            if (GATE == 2) {
 #pragma unroll
-                for (int j = 0; j < KJ; ++j) {
-                    const int c = lane + 32 * j;
-                    const float z = a.g[row * K + c] + (a.dt_bias ? a.dt_bias[h * K + c] : 0.f);
-                    float gz, gA;
-                    act_grad(z, eA, a.lower_bound, gz, gA);
-                    const float up = a.dg[row * K + c];
-                    const float dz = up * gz;
-                    a.dg[row * K + c] = dz;
-                    accz[j] += dz;
-                    accA = fmaf(up, gA, accA);
+        for (int u = 0; u < 2; ++u) {
+            if (!in[u]) continue;
+            const size_t row = (size_t)(t0 + u * PW) * H + h;
+            if (a.qk_norm) {
+#pragma unroll
+                for (int w = 0; w < 2; ++w) {
+                    float(&x)[EL] = w ? xk[u] : xq[u];
+                    float(&d)[EL] = w ? dk[u] : dq[u];
+                    const float r = row_rnorm<EL>(x, a.eps);
+                    float dot = 0.f;
+#pragma unroll
+                    for (int e = 0; e < EL; ++e) dot = fmaf(x[e] * r, d[e], dot);
+                    dot = warp_sum(dot);
+#pragma unroll
+                    for (int e = 0; e < EL; ++e) d[e] = r * (d[e] - x[e] * r * dot);
+                    stv(static_cast<TI*>(w ? a.dk : a.dq) + row * K + c0, d);
                 }
-            } else if (lane == 0) {
-                const float z = a.g[row] + (a.dt_bias ? a.dt_bias[h] : 0.f);
-                float gz, gA;
-                act_grad(z, eA, a.lower_bound, gz, gA);
-                const float up = a.dg[row];
-                const float dz = up * gz;
-                a.dg[row] = dz;
-                accz[0] += dz;
-                accA = fmaf(up, gA, accA);
+            }
+            if (gated) {
+                const int ne = (GATE == 2) ? EL : (lane == 0 ? 1 : 0);
+#pragma unroll
+                for (int e = 0; e < EL; ++e) {
+                    if (e >= ne) break;
+                    float gz, gA;
+                    act_grad(zg[u][e] + db[e], eA, a.lower_bound, gz, gA);
+                    const float dz = ug[u][e] * gz;
+                    accA = fmaf(ug[u][e], gA, accA);
+                    accz[e] += dz;
+                    ug[u][e] = dz;
+                }
+                if (GATE == 2) stv(a.dg + row * K + c0, ug[u]);
+                else if (lane == 0) a.dg[row] = ug[u][0];
             }
         }
     }
@@ -152,7 +213,7 @@ __global__ void __launch_bounds__(32 * PW) k_epilogue(int Ttot, int H, EpilogueA
     // partial sums of this token block: per channel (dt_bias) and per head (A_log)
     constexpr int NC = (GATE == 2) ? K : 1;
 #pragma unroll
-    for (int j = 0; j < KJ; ++j) sZ[warp][lane + 32 * j] = accz[j];
+    for (int e = 0; e < EL; ++e) sZ[warp][c0 + e] = accz[e];
     accA = warp_sum(accA);
     if (lane == 0) sAp[warp] = accA;
     __syncthreads();
