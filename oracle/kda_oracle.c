@@ -18,6 +18,15 @@
  *     S_t  = S~ + k_t r_t^T            write
  *     o_t  = S_t^T (scale q_t)         read, after the write
  *
+ * GatedDeltaNet-2 ("GatedDeltaNet-2 (NVlabs) — official spec transcription",
+ * §3, the per-token body) replaces the scalar beta by an erase vector b on the
+ * key axis and a write vector w on the value axis:
+ *
+ *     p_t  = S~^T (b_t .* k_t)         erase
+ *     r_t  = w_t .* v_t - p_t          write value
+ *
+ * (b = w = beta 1 gives the rule above), with the same write and read steps.
+ *
  * with S_{-1} = h0 (or 0) and ht = S_{L-1}. The operator family is the gate
  * choice of the ReWY paper's Table 1 (hub.valency.io W_esyzsyuq, "Delta-rule
  * operators"): DeltaNet has no decay, GDN a scalar decay, KDA a vector decay.
@@ -33,6 +42,12 @@
  *     forget:   dg_t   = rowsum(S~bar .* S~)  (d a / d g = a is folded in;
  *                                              scalar gate: summed over K)
  *               Sbar   = diag(a_t) S~bar
+ *
+ * and for GatedDeltaNet-2, in place of the correct and predict lines:
+ *
+ *     correct:  dv_t = w_t .* rbar ;   dw_t = rbar .* v_t ;   pbar = -rbar
+ *     predict:  S~bar = Sbar + (b_t .* k_t) pbar^T ;  u = S~ pbar ;
+ *               db_t = k_t .* u ;      dk_t += b_t .* u
  *
  * starting from Sbar = dht (or 0); after the first token dh0 = Sbar. The loss
  * whose gradients these are is <do, o> + <dht, ht>.
@@ -69,6 +84,9 @@ typedef struct {
     int backward;
     const int32_t *items;    /* optional list of (seq, head) pairs, 2 ints each */
     int n_items;             /* number of pairs in items (0: all pairs) */
+    const double *erase;     /* [T, H, K] or NULL: GatedDeltaNet-2 erase vector (beta unused) */
+    const double *write;     /* [T, H, V]: GatedDeltaNet-2 write vector (with erase) */
+    double *derase, *dwrite; /* their gradients (backward, with erase) */
 } oracle_problem;
 
 typedef struct {
@@ -98,14 +116,18 @@ static void step_fwd(const oracle_problem *p, int64_t t, int h, double *S, doubl
     const double *kt = p->k + (t * H + h) * (int64_t)K;
     const double *qt = p->q + (t * H + h) * (int64_t)K;
     const double *vt = p->v + (t * H + h) * (int64_t)V;
-    double bt = p->beta[t * H + h];
+    const double *bv = p->erase ? p->erase + (t * H + h) * (int64_t)K : NULL;
+    const double *wv = p->erase ? p->write + (t * H + h) * (int64_t)V : NULL;
+    double bt = p->erase ? 0.0 : p->beta[t * H + h];
     decay(p, t, h, a);
     for (int i = 0; i < K; ++i)
         for (int j = 0; j < V; ++j) S[i * V + j] *= a[i];
     for (int j = 0; j < V; ++j) pv[j] = 0.0;
-    for (int i = 0; i < K; ++i)
-        for (int j = 0; j < V; ++j) pv[j] += S[i * V + j] * kt[i];
-    for (int j = 0; j < V; ++j) r[j] = bt * (vt[j] - pv[j]);
+    for (int i = 0; i < K; ++i) {
+        double ke = bv ? bv[i] * kt[i] : kt[i];
+        for (int j = 0; j < V; ++j) pv[j] += S[i * V + j] * ke;
+    }
+    for (int j = 0; j < V; ++j) r[j] = bv ? wv[j] * vt[j] - pv[j] : bt * (vt[j] - pv[j]);
     for (int i = 0; i < K; ++i)
         for (int j = 0; j < V; ++j) S[i * V + j] += kt[i] * r[j];
     if (o) {
@@ -127,7 +149,9 @@ static void step_bwd(const oracle_problem *p, int64_t t, int h, const double *Sp
     const double *qt = p->q + (t * H + h) * (int64_t)K;
     const double *vt = p->v + (t * H + h) * (int64_t)V;
     const double *dot = p->dout + (t * H + h) * (int64_t)V;
-    double bt = p->beta[t * H + h];
+    const double *bv = p->erase ? p->erase + (t * H + h) * (int64_t)K : NULL;
+    const double *wv = p->erase ? p->write + (t * H + h) * (int64_t)V : NULL;
+    double bt = p->erase ? 0.0 : p->beta[t * H + h];
     double *dqt = p->dq + (t * H + h) * (int64_t)K;
     double *dkt = p->dk + (t * H + h) * (int64_t)K;
     double *dvt = p->dv + (t * H + h) * (int64_t)V;
@@ -137,9 +161,11 @@ static void step_bwd(const oracle_problem *p, int64_t t, int h, const double *Sp
     for (int i = 0; i < K; ++i)
         for (int j = 0; j < V; ++j) St[i * V + j] = a[i] * Sprev[i * V + j];   /* S~ */
     for (int j = 0; j < V; ++j) pv[j] = 0.0;
-    for (int i = 0; i < K; ++i)
-        for (int j = 0; j < V; ++j) pv[j] += St[i * V + j] * kt[i];
-    for (int j = 0; j < V; ++j) r[j] = bt * (vt[j] - pv[j]);
+    for (int i = 0; i < K; ++i) {
+        double ke = bv ? bv[i] * kt[i] : kt[i];
+        for (int j = 0; j < V; ++j) pv[j] += St[i * V + j] * ke;
+    }
+    for (int j = 0; j < V; ++j) r[j] = bv ? wv[j] * vt[j] - pv[j] : bt * (vt[j] - pv[j]);
 
     /* read: o = S_t^T (scale q), S_t = S~ + k r^T */
     for (int i = 0; i < K; ++i) {
@@ -160,22 +186,43 @@ static void step_bwd(const oracle_problem *p, int64_t t, int h, const double *Sp
     for (int j = 0; j < V; ++j) rbar[j] = 0.0;
     for (int i = 0; i < K; ++i)
         for (int j = 0; j < V; ++j) rbar[j] += Sbar[i * V + j] * kt[i];
-    /* correct: r = beta (v - p) */
-    double db = 0.0;
-    for (int j = 0; j < V; ++j) {
-        dvt[j] = bt * rbar[j];
-        db += rbar[j] * (vt[j] - pv[j]);
-    }
-    p->dbeta[t * H + h] = db;
-    /* predict: p = S~^T k ; pbar = -beta rbar (reuse rbar as pbar) */
-    for (int j = 0; j < V; ++j) rbar[j] = -bt * rbar[j];
-    for (int i = 0; i < K; ++i) {
-        double acc = 0.0;
+    if (bv) {
+        /* correct: r = w .* v - p */
+        double *dwt = p->dwrite + (t * H + h) * (int64_t)V;
+        double *dbt = p->derase + (t * H + h) * (int64_t)K;
         for (int j = 0; j < V; ++j) {
-            Sbar[i * V + j] += kt[i] * rbar[j];          /* S~bar */
-            acc += St[i * V + j] * rbar[j];
+            dvt[j] = wv[j] * rbar[j];
+            dwt[j] = rbar[j] * vt[j];
+            rbar[j] = -rbar[j];                          /* pbar */
         }
-        dkt[i] += acc;
+        /* erase: p = S~^T (b .* k) */
+        for (int i = 0; i < K; ++i) {
+            double u = 0.0, ke = bv[i] * kt[i];
+            for (int j = 0; j < V; ++j) {
+                Sbar[i * V + j] += ke * rbar[j];         /* S~bar */
+                u += St[i * V + j] * rbar[j];
+            }
+            dbt[i] = kt[i] * u;
+            dkt[i] += bv[i] * u;
+        }
+    } else {
+        /* correct: r = beta (v - p) */
+        double db = 0.0;
+        for (int j = 0; j < V; ++j) {
+            dvt[j] = bt * rbar[j];
+            db += rbar[j] * (vt[j] - pv[j]);
+        }
+        p->dbeta[t * H + h] = db;
+        /* predict: p = S~^T k ; pbar = -beta rbar (reuse rbar as pbar) */
+        for (int j = 0; j < V; ++j) rbar[j] = -bt * rbar[j];
+        for (int i = 0; i < K; ++i) {
+            double acc = 0.0;
+            for (int j = 0; j < V; ++j) {
+                Sbar[i * V + j] += kt[i] * rbar[j];      /* S~bar */
+                acc += St[i * V + j] * rbar[j];
+            }
+            dkt[i] += acc;
+        }
     }
     /* forget: S~ = diag(a) S_{t-1} */
     if (p->gate == 2) {
@@ -267,11 +314,11 @@ static void *worker(void *arg) {
  * an allocation failure, 2 on invalid arguments. */
 int kda_oracle_run(const oracle_problem *p, int nthreads) {
     if (!p || p->n_seq < 0 || p->H <= 0 || p->K <= 0 || p->V <= 0 || !p->seq_start ||
-        !p->q || !p->k || !p->v || !p->beta || !p->o || (p->gate != 0 && !p->g) ||
-        p->gate < 0 || p->gate > 2)
+        !p->q || !p->k || !p->v || (!p->beta && !p->erase) || (p->erase && !p->write) || !p->o ||
+        (p->gate != 0 && !p->g) || p->gate < 0 || p->gate > 2)
         return 2;
-    if (p->backward && (!p->dout || !p->dq || !p->dk || !p->dv || !p->dbeta ||
-                        (p->gate != 0 && !p->dg)))
+    if (p->backward && (!p->dout || !p->dq || !p->dk || !p->dv || (!p->erase && !p->dbeta) ||
+                        (p->erase && (!p->derase || !p->dwrite)) || (p->gate != 0 && !p->dg)))
         return 2;
     if (nthreads < 1) nthreads = 1;
     if (nthreads > 256) nthreads = 256;

@@ -49,6 +49,8 @@ class _Problem(ctypes.Structure):
         ("backward", ctypes.c_int),
         ("items", ctypes.c_void_p),
         ("n_items", ctypes.c_int),
+        ("erase", ctypes.c_void_p), ("write", ctypes.c_void_p),
+        ("derase", ctypes.c_void_p), ("dwrite", ctypes.c_void_p),
     ]
 
 
@@ -77,7 +79,7 @@ def _c64(a):
 
 def run_recurrence(q, k, v, beta, g, seq_start, *, gate: str, scale: float, h0=None,
                    do=None, dht=None, backward: bool = True, nthreads: int | None = None,
-                   items=None) -> dict:
+                   items=None, erase=None, write=None) -> dict:
     """Run the oracle on packed arrays.
 
     q, k: [T, H, K]; v, do: [T, H, V]; beta: [T, H]; g: [T, H] (scalar),
@@ -85,11 +87,14 @@ def run_recurrence(q, k, v, beta, g, seq_start, *, gate: str, scale: float, h0=N
     seq_start: N + 1 token offsets. ``items``: optional list of (seq, head)
     pairs to compute (outputs of other pairs are left at zero).
     Returns float64 arrays o, ht and, with ``backward``, dq, dk, dv, dbeta, dg
-    (None without a gate) and dh0.
+    (None without a gate) and dh0. GatedDeltaNet-2: ``erase`` [T, H, K] and
+    ``write`` [T, H, V] replace beta (which may then be None); the backward
+    then returns derase and dwrite in place of dbeta.
     """
     lib = _load()
     q, k, v, beta = _c64(q), _c64(k), _c64(v), _c64(beta)
     g, h0, do, dht = _c64(g), _c64(h0), _c64(do), _c64(dht)
+    erase, write = _c64(erase), _c64(write)
     T, H, K = q.shape
     V = v.shape[2]
     ss = np.ascontiguousarray(np.asarray(seq_start, dtype=np.int64))
@@ -99,8 +104,10 @@ def run_recurrence(q, k, v, beta, g, seq_start, *, gate: str, scale: float, h0=N
         if do is None:
             raise ValueError("backward needs do")
         out.update(dq=np.zeros((T, H, K)), dk=np.zeros((T, H, K)), dv=np.zeros((T, H, V)),
-                   dbeta=np.zeros((T, H)), dh0=np.zeros((N, H, K, V)),
+                   dbeta=None if erase is not None else np.zeros((T, H)), dh0=np.zeros((N, H, K, V)),
                    dg=None if gate == "none" else np.zeros(g.shape))
+        if erase is not None:
+            out.update(derase=np.zeros((T, H, K)), dwrite=np.zeros((T, H, V)))
     it = None
     n_items = 0
     if items is not None:
@@ -111,10 +118,13 @@ def run_recurrence(q, k, v, beta, g, seq_start, *, gate: str, scale: float, h0=N
     p.gate, p.scale = _GATES[gate], float(scale)
     p.q, p.k, p.v, p.beta, p.g, p.h0 = _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(h0)
     p.dout, p.dht = _ptr(do), _ptr(dht)
+    p.erase, p.write = _ptr(erase), _ptr(write)
     p.o, p.ht = _ptr(out["o"]), _ptr(out["ht"])
     if backward:
         p.dq, p.dk, p.dv = _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"])
         p.dbeta, p.dg, p.dh0 = _ptr(out["dbeta"]), _ptr(out["dg"]), _ptr(out["dh0"])
+        if erase is not None:
+            p.derase, p.dwrite = _ptr(out["derase"]), _ptr(out["dwrite"])
     p.backward = 1 if backward else 0
     p.items = None if it is None else it.ctypes.data
     p.n_items = n_items
