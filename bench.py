@@ -265,10 +265,15 @@ def run_ours(args):
     if args.prologue:
         case_cpu, pro = with_prologue(case_cpu)
         pro = {k: v.to(dev) for k, v in pro.items()}
+    if args.gdn2:
+        import torch as _t
+        gen = _t.Generator().manual_seed(4242)
+        pro["erase"] = (2.0 * _t.sigmoid(_t.randn(case_cpu.k.shape, generator=gen))).to(case_cpu.q.dtype).to(dev)
+        pro["write"] = _t.sigmoid(_t.randn(case_cpu.v.shape, generator=gen)).to(case_cpu.q.dtype).to(dev)
     case = case_cpu.to(dev)
     lib = _lib.load()
     save = 1 if args.policy == "save" else 0
-    p = kda.make_problem(case.q, case.k, case.v, case.g, case.beta, gate=case.gate,
+    p = kda.make_problem(case.q, case.k, case.v, case.g, None if args.gdn2 else case.beta, gate=case.gate,
                          scale=case.scale, initial_state=case.h0, cu_seqlens=case.cu_seqlens,
                          save_policy=save, qk_l2norm=bool(args.prologue), **pro)
     wf = torch.empty(kda.kda_workspace_size(p, False), dtype=torch.uint8, device=dev)
@@ -379,10 +384,10 @@ def run_ours(args):
         kernels[k] = rec
 
     e2e = None
-    if not args.no_e2e and not args.prologue:   # (the end-to-end and CPU legs time the headline problem)
+    if not args.no_e2e and not args.prologue and not args.gdn2:   # (the end-to-end and CPU legs time the headline problem)
         e2e = run_e2e(args, case_cpu, dev, kda, K)
     cpu = None
-    if rank == 0 and ws == 1 and not args.no_cpu and not args.prologue:
+    if rank == 0 and ws == 1 and not args.no_cpu and not args.prologue and not args.gdn2:
         cpu = cpu_baseline(case_cpu)
 
     if rank == 0:
@@ -396,6 +401,9 @@ def run_ours(args):
                        "policy": args.policy, "parallelism": f"replicas x{ws}",
                        "prologue": ("raw gate activated in the operator (softplus form, A_log, dt_bias) and "
                                     "q/k L2-normalised in the operator") if args.prologue else "off",
+                       "rule": ("GatedDeltaNet-2: erase b = 2 sigmoid(N(0,1)) per key channel, write w = "
+                                "sigmoid(N(0,1)) per value channel (fp32 CUDA-core chunk kernels)") if args.gdn2
+                       else "delta rule with beta",
                        "l2": "flushed by a 256 MiB write before every timed step"},
             "tflops": round(tflops, 2), "tflops_executed": round(tflops_exec, 2),
             "frac_bf16_peak": round(tflops / pk["bf16"], 4),
@@ -618,6 +626,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--heads", type=int, default=0, help="restrict the workload to its first H heads (profiling)")
+    ap.add_argument("--gdn2", action="store_true",
+                    help="the GatedDeltaNet-2 rule (erase/write vectors in place of beta)")
     ap.add_argument("--prologue", action="store_true",
                     help="raw gate and unnormalised q, k: activation and L2 norm inside the operator")
     ap.add_argument("--decode", action="store_true",

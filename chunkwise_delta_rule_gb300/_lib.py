@@ -42,6 +42,8 @@ class KdaProblem(ctypes.Structure):
         ("lower_bound", ctypes.c_float),
         ("qk_l2norm", ctypes.c_int),
         ("l2norm_eps", ctypes.c_float),
+        ("erase", ctypes.c_void_p),
+        ("write", ctypes.c_void_p),
     ]
 
 
@@ -72,7 +74,7 @@ def load() -> ctypes.CDLL:
     lib.kda_saved_size.restype = sz
     lib.kda_chunk_fwd.argtypes = [P, vp, vp, vp, vp, sz, vp]
     lib.kda_chunk_fwd.restype = ctypes.c_int
-    lib.kda_chunk_bwd.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.kda_chunk_bwd.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.kda_chunk_bwd.restype = ctypes.c_int
     lib.kda_device_status.argtypes = [P, vp, sz, vp, ctypes.POINTER(ctypes.c_int32)]
     lib.kda_device_status.restype = ctypes.c_int

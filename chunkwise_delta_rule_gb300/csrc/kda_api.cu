@@ -37,6 +37,8 @@ kda_status check_dims(const kda_problem* p, Dims& d) {
     if (p->save_policy != 0 && p->save_policy != 1)
         return fail(KDA_ERR_INVALID_ARG, "save_policy must be 0 or 1");
     if (p->qk_l2norm != 0 && p->qk_l2norm != 1) return fail(KDA_ERR_INVALID_ARG, "qk_l2norm must be 0 or 1");
+    if ((p->erase == nullptr) != (p->write == nullptr))
+        return fail(KDA_ERR_INVALID_ARG, "erase and write come together (GatedDeltaNet-2)");
     if (p->A_log && p->gate == KDA_GATE_NONE) return fail(KDA_ERR_INVALID_ARG, "A_log needs a gate");
     if (p->dt_bias && !p->A_log) return fail(KDA_ERR_INVALID_ARG, "dt_bias needs A_log");
     if (p->A_log && !(p->lower_bound == 0.f || (p->lower_bound >= -5.f && p->lower_bound < 0.f)))
@@ -68,7 +70,7 @@ struct Layout {
 
 // The tensor-core path serves bf16 I/O at K = V = 128; everything else runs
 // the fp32 CUDA-core kernels.
-bool use_tc(const kda_problem* p) { return p->io == KDA_BF16 && p->K == 128; }
+bool use_tc(const kda_problem* p) { return p->io == KDA_BF16 && p->K == 128 && !p->erase; }
 
 Layout layout(const Dims& d) {
     Layout L;
@@ -217,8 +219,8 @@ size_t prologue_bytes(const kda_problem* p, const Dims& d, bool bwd) {
 }
 
 kda_status check_inputs(const kda_problem* p, const Dims& d) {
-    if (d.Ttot > 0 && (!p->q || !p->k || !p->v || !p->beta))
-        return fail(KDA_ERR_INVALID_ARG, "q, k, v and beta must be non-NULL");
+    if (d.Ttot > 0 && (!p->q || !p->k || !p->v || (!p->beta && !p->erase)))
+        return fail(KDA_ERR_INVALID_ARG, "q, k, v and beta (or erase and write) must be non-NULL");
     if (p->gate == KDA_GATE_NONE && p->g) return fail(KDA_ERR_INVALID_ARG, "g must be NULL without a gate");
     if (p->gate != KDA_GATE_NONE && !p->g && d.Ttot > 0)
         return fail(KDA_ERR_INVALID_ARG, "g must be non-NULL with a gate");
@@ -326,7 +328,7 @@ void set_last_error(const char* msg) { g_err = msg; }
 
 extern "C" {
 
-int kda_abi_version(void) { return 2; }
+int kda_abi_version(void) { return 3; }
 
 const char* kda_last_error(void) { return g_err.c_str(); }
 
@@ -415,7 +417,8 @@ static kda_status chunk_fwd_core(const kda_problem* p, void* o, float* ht, void*
     } else {
         carve_fwd(cw, d, f, false);
     }
-    e = traced("k_prep", cs, [&] { return kda::launch_prep(s, bf16, (int)p->gate, p->q, p->k, p->v, p->beta, p->g, t, f, cs); });
+    e = traced("k_prep", cs, [&] { return kda::launch_prep(s, bf16, (int)p->gate, p->q, p->k, p->v, p->beta, p->g, t, f, cs,
+                                                                                  kda::Gdn2{p->erase, p->write}); });
     if (e != cudaSuccess) return cuda_fail(e, "prep");
     e = traced("k_fwd_scan", cs, [&] { return kda::launch_fwd_scan(s, bf16, p->save_policy ? 3 : 1, p->h0, t, f, o, ht, cs); });
     if (e != cudaSuccess) return cuda_fail(e, "forward scan");
@@ -423,14 +426,17 @@ static kda_status chunk_fwd_core(const kda_problem* p, void* o, float* ht, void*
 }
 
 static kda_status chunk_bwd_core(const kda_problem* p, const void* dout, const float* dht, const void* saved,
-                                 void* dq, void* dk, void* dv, float* dg, void* dbeta, float* dh0, void* ws,
-                                 size_t ws_bytes, kda_stream_t stream) {
+                                 void* dq, void* dk, void* dv, float* dg, void* dbeta, void* derase, void* dwrite,
+                                 float* dh0, void* ws, size_t ws_bytes, kda_stream_t stream) {
     Dims d;
     kda_status st = check_dims(p, d);
     if (st != KDA_OK) return st;
     if ((st = check_inputs(p, d)) != KDA_OK) return st;
-    if (d.Ttot > 0 && (!dout || !dq || !dk || !dv || !dbeta))
+    if (d.Ttot > 0 && (!dout || !dq || !dk || !dv || (!p->erase && !dbeta)))
         return fail(KDA_ERR_INVALID_ARG, "dout, dq, dk, dv and dbeta must be non-NULL");
+    if (d.Ttot > 0 && p->erase && (!derase || !dwrite))
+        return fail(KDA_ERR_INVALID_ARG, "derase and dwrite must be non-NULL with erase and write");
+    const kda::Gdn2 gd{p->erase, p->write, derase, dwrite};
     if (p->gate == KDA_GATE_NONE && dg) return fail(KDA_ERR_INVALID_ARG, "dg must be NULL without a gate");
     if (p->gate != KDA_GATE_NONE && !dg && d.Ttot > 0)
         return fail(KDA_ERR_INVALID_ARG, "dg must be non-NULL with a gate");
@@ -507,16 +513,17 @@ static kda_status chunk_bwd_core(const kda_problem* p, const void* dout, const f
     cudaError_t e = traced("k_table", cs, [&] { return kda::launch_table(s, p->B, p->T, p->cu_seqlens, t, cs); });
     if (e != cudaSuccess) return cuda_fail(e, "chunk table");
     if (!p->save_policy) {
-        e = traced("k_prep", cs, [&] { return kda::launch_prep(s, bf16, (int)p->gate, p->q, p->k, p->v, p->beta, p->g, t, f, cs); });
+        e = traced("k_prep", cs, [&] { return kda::launch_prep(s, bf16, (int)p->gate, p->q, p->k, p->v, p->beta, p->g, t, f, cs,
+                                                                                  kda::Gdn2{p->erase, p->write}); });
         if (e != cudaSuccess) return cuda_fail(e, "prep (recompute)");
         e = traced("k_fwd_scan_recompute", cs, [&] { return kda::launch_fwd_scan(s, bf16, 2, p->h0, t, f, nullptr, nullptr, cs); });
         if (e != cudaSuccess) return cuda_fail(e, "forward scan (recompute)");
     }
     e = traced("k_bwd_scan", cs, [&] { return kda::launch_bwd_scan(s, bf16, dout, dht, t, f, b, dh0, cs); });
     if (e != cudaSuccess) return cuda_fail(e, "reverse scan");
-    e = traced("k_bwd_dstate", cs, [&] { return kda::launch_bwd_dstate(s, bf16, dout, p->v, p->beta, t, f, b, dv, cs); });
+    e = traced("k_bwd_dstate", cs, [&] { return kda::launch_bwd_dstate(s, bf16, dout, p->v, p->beta, t, f, b, dv, cs, gd); });
     if (e != cudaSuccess) return cuda_fail(e, "state-gradient consumer");
-    e = traced("k_bwd_intra", cs, [&] { return kda::launch_bwd_intra(s, bf16, (int)p->gate, p->q, p->k, p->beta, p->g, t, f, b, dq, dk, dbeta, dg, cs); });
+    e = traced("k_bwd_intra", cs, [&] { return kda::launch_bwd_intra(s, bf16, (int)p->gate, p->q, p->k, p->beta, p->g, t, f, b, dq, dk, dbeta, dg, cs, gd); });
     if (e != cudaSuccess) return cuda_fail(e, "intra consumer");
     return KDA_OK;
 }
@@ -567,10 +574,10 @@ kda_status kda_chunk_fwd(const kda_problem* p, void* o, float* ht, void* saved, 
 }
 
 kda_status kda_chunk_bwd(const kda_problem* p, const void* dout, const float* dht, const void* saved, void* dq,
-                         void* dk, void* dv, float* dg, void* dbeta, float* dh0, float* dA_log, float* ddt_bias,
-                         void* ws, size_t ws_bytes, kda_stream_t stream) {
+                         void* dk, void* dv, float* dg, void* dbeta, void* derase, void* dwrite, float* dh0,
+                         float* dA_log, float* ddt_bias, void* ws, size_t ws_bytes, kda_stream_t stream) {
     if (!p || !has_prologue(p))
-        return chunk_bwd_core(p, dout, dht, saved, dq, dk, dv, dg, dbeta, dh0, ws, ws_bytes, stream);
+        return chunk_bwd_core(p, dout, dht, saved, dq, dk, dv, dg, dbeta, derase, dwrite, dh0, ws, ws_bytes, stream);
     Dims d;
     kda_status st = check_dims(p, d);
     if (st != KDA_OK) return st;
@@ -585,13 +592,13 @@ kda_status kda_chunk_bwd(const kda_problem* p, const void* dout, const float* dh
         if (e == cudaSuccess && ddt_bias)
             e = cudaMemsetAsync(ddt_bias, 0, sizeof(float) * d.H * (p->gate == KDA_GATE_CHANNEL ? d.D : 1), cs);
         if (e != cudaSuccess) return cuda_fail(e, "zero parameter gradients");
-        return chunk_bwd_core(&c, dout, dht, saved, dq, dk, dv, dg, dbeta, dh0, ws, ws_bytes, stream);
+        return chunk_bwd_core(&c, dout, dht, saved, dq, dk, dv, dg, dbeta, derase, dwrite, dh0, ws, ws_bytes, stream);
     }
     const size_t core = core_workspace(&c, d, 1);
     if ((st = check_ws(ws, ws_bytes, core + prologue_bytes(p, d, true))) != KDA_OK) return st;
     char* w = static_cast<char*>(ws) + core;
     if ((st = run_prologue(p, d, w, c, cs)) != KDA_OK) return st;
-    st = chunk_bwd_core(&c, dout, dht, saved, dq, dk, dv, dg, dbeta, dh0, ws, core, stream);
+    st = chunk_bwd_core(&c, dout, dht, saved, dq, dk, dv, dg, dbeta, derase, dwrite, dh0, ws, core, stream);
     if (st != KDA_OK) return st;
     // the prologue's buffers, then the partial sums
     const size_t es = p->io == KDA_BF16 ? 2 : 4, tok = (size_t)d.Ttot * d.H * d.D;
@@ -637,7 +644,7 @@ kda_status kda_recurrent_fwd(const kda_problem* p, void* o, float* ht, int32_t* 
     cudaError_t e = traced("k_recurrent", cs, [&] {
         return kda::launch_recurrent(s, p->io == KDA_BF16, (int)p->gate, p->T, p->cu_seqlens, p->q, p->k, p->v, p->beta,
                                      p->g, p->h0, o, ht, err, p->A_log, p->dt_bias, p->lower_bound, p->qk_l2norm,
-                                     l2eps(p), cs);
+                                     l2eps(p), cs, kda::Gdn2{p->erase, p->write});
     });
     if (e != cudaSuccess) return cuda_fail(e, "recurrent forward");
     return KDA_OK;

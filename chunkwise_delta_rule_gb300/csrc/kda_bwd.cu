@@ -36,7 +36,7 @@ __device__ __forceinline__ void dstate_chunk(int c, int h, const Shape& s, const
                                              const TI* __restrict__ v, const TI* __restrict__ beta, const Table& t,
                                              const IT* __restrict__ Pin, const IT* __restrict__ Rin,
                                              const IT* __restrict__ Sin, const IT* __restrict__ SBin, const Bwd& b,
-                                             TI* __restrict__ dv) {
+                                             TI* __restrict__ dv, const Gdn2& gd) {
     constexpr int LD = D + 1, LS = SL + 1;
     extern __shared__ float smem[];
     float* sO = smem;              // [BT][LD] dO
@@ -64,16 +64,22 @@ __device__ __forceinline__ void dstate_chunk(int c, int h, const Shape& s, const
         sR[r * LD + col] = ld(R + e);
     }
     __syncthreads();
-    // dv = beta P and <v_i, P_i>, one warp per row
+    // dv = beta P and <v_i, P_i>, one warp per row (GatedDeltaNet-2: dv = w .* P, dw = v .* P)
+    const TI* wr = static_cast<const TI*>(gd.write);
     for (int r = warp; r < BT; r += NTHREADS / 32) {
         float acc = 0.f;
         if (r < len) {
             const size_t tok = (size_t)(tok0 + r) * H + h;
-            const float bt = ld(beta + tok);
+            const float bt = wr ? 0.f : ld(beta + tok);
             for (int col = lane; col < D; col += 32) {
-                const float p = sP[r * LD + col];
-                acc = fmaf(ld(v + tok * D + col), p, acc);
-                st(dv + tok * D + col, bt * p);
+                const float p = sP[r * LD + col], vv = ld(v + tok * D + col);
+                if (wr) {
+                    st(dv + tok * D + col, ld(wr + tok * D + col) * p);
+                    st(static_cast<TI*>(gd.dwrite) + tok * D + col, vv * p);
+                } else {
+                    acc = fmaf(vv, p, acc);
+                    st(dv + tok * D + col, bt * p);
+                }
             }
         }
 #pragma unroll
@@ -152,7 +158,7 @@ __device__ __forceinline__ void intra_chunk(int c, int h, const Shape& s, const 
                                             const TI* __restrict__ k, const TI* __restrict__ beta,
                                             const float* __restrict__ g, const Table& t, const Bwd& b,
                                             TI* __restrict__ dq, TI* __restrict__ dk, TI* __restrict__ dbeta,
-                                            float* __restrict__ dg) {
+                                            float* __restrict__ dg, const Gdn2& gd) {
     constexpr int LD = D + 1, LA = BT + 1;
     extern __shared__ float smem[];
     float* sK = smem;               // [BT][LD] keys
@@ -197,7 +203,12 @@ __device__ __forceinline__ void intra_chunk(int c, int h, const Shape& s, const 
             sHQ[(idx / BT) * LA + idx % BT] = HQ[idx];
         }
     }
-    if (tid < BT) sBeta[tid] = (tid < len) ? ld(beta + (size_t)(tok0 + tid) * H + h) : 0.f;
+    if (tid < BT) sBeta[tid] = (tid < len && !gd.erase) ? ld(beta + (size_t)(tok0 + tid) * H + h) : 0.f;
+    // GatedDeltaNet-2: the erase vector takes beta's place on the key side (E = b .* K exp(G))
+    const TI* er = static_cast<const TI*>(gd.erase);
+    auto ebeta = [&](int r, int col) {
+        return er ? ((r < len) ? ld(er + ((size_t)(tok0 + r) * H + h) * D + col) : 0.f) : sBeta[r];
+    };
     __syncthreads();
     int wide_col = 0;
     if (tid < D) {
@@ -263,7 +274,7 @@ __device__ __forceinline__ void intra_chunk(int c, int h, const Shape& s, const 
         for (int idx = tid; idx < BT * D; idx += NTHREADS) {
             const int r = idx / D, col = idx % D;
             const float a = alpha(r, col);
-            sF3[r * LD + col] = sBeta[r] * sK[r * LD + col] * a;
+            sF3[r * LD + col] = ebeta(r, col) * sK[r * LD + col] * a;
             sF4[r * LD + col] = scale * sQ[r * LD + col] * a;
         }
         __syncthreads();
@@ -340,7 +351,7 @@ __device__ __forceinline__ void intra_chunk(int c, int h, const Shape& s, const 
                 float e = 0.f;
                 if (i >= ra + BC) e = exp2f(sG[i * LD + col] - sG[re * LD + col]);
                 else if (i >= ra) e = exp2f(sG[i * LD + col] - sG[rm * LD + col]);
-                sF3[i * LD + col] = sBeta[i] * sK[i * LD + col] * e;
+                sF3[i * LD + col] = ebeta(i, col) * sK[i * LD + col] * e;
                 sF4[i * LD + col] = scale * sQ[i * LD + col] * e;
             }
             __syncthreads();
@@ -404,11 +415,12 @@ __device__ __forceinline__ void intra_chunk(int c, int h, const Shape& s, const 
             const float Qt = aQ[ii][jj] + gam * QS[o];                    // gamma * Q_g_bar
             const float Et = aE[ii][jj] + gam * PS[o];                    // gamma * E_bar
             const float Yt = aY[ii][jj] + FB[o] * exp2f(gl2[col] - gm);   // Y_bar / gamma
-            const float kv = sK[m * LD + col], qv = sQ[m * LD + col], bt = sBeta[m];
+            const float kv = sK[m * LD + col], qv = sQ[m * LD + col], bt = ebeta(m, col);
             if (m < len) {
                 const size_t go = ((size_t)(tok0 + m) * H + h) * D + col;
                 st(dq + go, scale * Qt);
                 st(dk + go, bt * Et + Yt);
+                if (er) st(static_cast<TI*>(gd.derase) + go, kv * Et);   // db = K exp(G) .* E_bar
             }
             rowacc[ii] = fmaf(kv, Et, rowacc[ii]);
             sF4[m * LD + col] = scale * qv * Qt + bt * kv * Et - kv * Yt;  // G_bar
@@ -421,7 +433,7 @@ __device__ __forceinline__ void intra_chunk(int c, int h, const Shape& s, const 
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
         const int m = TK::row(ii);
-        if (lane == 0 && m < len)
+        if (lane == 0 && m < len && !er)
             st(dbeta + (size_t)(tok0 + m) * H + h, x + b.DBW[ch * BT + m]);
     }
     (void)warp;
@@ -471,16 +483,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     k_bwd_dstate(Shape s, const TI* __restrict__ dout, const TI* __restrict__ v,
                  const TI* __restrict__ beta, Table t, const IT* __restrict__ Pin,
                  const IT* __restrict__ Rin, const IT* __restrict__ Sin, const IT* __restrict__ SBin,
-                 const int32_t* __restrict__ list, Bwd b, TI* __restrict__ dv) {
+                 const int32_t* __restrict__ list, Bwd b, TI* __restrict__ dv, Gdn2 gd) {
     if (list) {
         const int cnt = list[0];
         for (int w = blockIdx.x; w < cnt; w += gridDim.x) {
             const int ch = list[1 + w];
-            dstate_chunk<TI, IT, D>(ch / s.H, ch % s.H, s, dout, v, beta, t, Pin, Rin, Sin, SBin, b, dv);
+            dstate_chunk<TI, IT, D>(ch / s.H, ch % s.H, s, dout, v, beta, t, Pin, Rin, Sin, SBin, b, dv, gd);
             __syncthreads();
         }
     } else {
-        dstate_chunk<TI, IT, D>(blockIdx.x, blockIdx.y, s, dout, v, beta, t, Pin, Rin, Sin, SBin, b, dv);
+        dstate_chunk<TI, IT, D>(blockIdx.x, blockIdx.y, s, dout, v, beta, t, Pin, Rin, Sin, SBin, b, dv, gd);
     }
 }
 
@@ -489,23 +501,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     k_bwd_intra(Shape s, const TI* __restrict__ q, const TI* __restrict__ k,
                 const TI* __restrict__ beta, const float* __restrict__ g, Table t,
                 const int32_t* __restrict__ list, Bwd b, TI* __restrict__ dq, TI* __restrict__ dk,
-                TI* __restrict__ dbeta, float* __restrict__ dg) {
+                TI* __restrict__ dbeta, float* __restrict__ dg, Gdn2 gd) {
     if (list) {
         const int cnt = list[0];
         for (int w = blockIdx.x; w < cnt; w += gridDim.x) {
             const int ch = list[1 + w];
-            intra_chunk<TI, D, GATE>(ch / s.H, ch % s.H, s, q, k, beta, g, t, b, dq, dk, dbeta, dg);
+            intra_chunk<TI, D, GATE>(ch / s.H, ch % s.H, s, q, k, beta, g, t, b, dq, dk, dbeta, dg, gd);
             __syncthreads();
         }
     } else {
-        intra_chunk<TI, D, GATE>(blockIdx.x, blockIdx.y, s, q, k, beta, g, t, b, dq, dk, dbeta, dg);
+        intra_chunk<TI, D, GATE>(blockIdx.x, blockIdx.y, s, q, k, beta, g, t, b, dq, dk, dbeta, dg, gd);
     }
 }
 
 template <typename TI, typename IT, int D>
 cudaError_t run_dstate(const Shape& s, const void* dout, const void* v, const void* beta, Table t,
                        const IT* P, const IT* R, const IT* S, const IT* SB, const int32_t* list, Bwd b,
-                       void* dv, cudaStream_t st) {
+                       void* dv, cudaStream_t st, const Gdn2& gd = Gdn2{}) {
     constexpr int LD = D + 1, LS = SL + 1;
     constexpr size_t smem = sizeof(float) * (3 * BT * LD + 2 * D * LS);
     auto kern = k_bwd_dstate<TI, IT, D>;
@@ -513,14 +525,14 @@ cudaError_t run_dstate(const Shape& s, const void* dout, const void* v, const vo
     if (e != cudaSuccess) return e;
     const dim3 grid = list ? dim3(sm_count()) : dim3(s.NC, s.H);
     kern<<<grid, NTHREADS, smem, st>>>(s, (const TI*)dout, (const TI*)v, (const TI*)beta, t, P, R, S, SB,
-                                       list, b, (TI*)dv);
+                                       list, b, (TI*)dv, gd);
     return cudaGetLastError();
 }
 
 template <typename TI, int D, int GATE>
 cudaError_t run_intra(const Shape& s, const void* q, const void* k, const void* beta, const float* g,
                       Table t, const int32_t* list, Bwd b, void* dq, void* dk, void* dbeta, float* dg,
-                      cudaStream_t st) {
+                      cudaStream_t st, const Gdn2& gd) {
     constexpr int LD = D + 1, LA = BT + 1;
     constexpr size_t smem = sizeof(float) * (5 * BT * LD + 2 * BT * LA + 2 * BT + D);
     auto kern = k_bwd_intra<TI, D, GATE>;
@@ -528,41 +540,41 @@ cudaError_t run_intra(const Shape& s, const void* q, const void* k, const void* 
     if (e != cudaSuccess) return e;
     const dim3 grid = list ? dim3(sm_count()) : dim3(s.NC, s.H);
     kern<<<grid, NTHREADS, smem, st>>>(s, (const TI*)q, (const TI*)k, (const TI*)beta, g, t, list, b,
-                                       (TI*)dq, (TI*)dk, (TI*)dbeta, dg);
+                                       (TI*)dq, (TI*)dk, (TI*)dbeta, dg, gd);
     return cudaGetLastError();
 }
 
 template <typename TI, int D>
 cudaError_t run_intra_gate(int gate, const Shape& s, const void* q, const void* k, const void* beta,
                            const float* g, Table t, const int32_t* list, Bwd b, void* dq, void* dk,
-                           void* dbeta, float* dg, cudaStream_t st) {
+                           void* dbeta, float* dg, cudaStream_t st, const Gdn2& gd = Gdn2{}) {
     switch (gate) {
-        case 0: return run_intra<TI, D, 0>(s, q, k, beta, g, t, list, b, dq, dk, dbeta, dg, st);
-        case 1: return run_intra<TI, D, 1>(s, q, k, beta, g, t, list, b, dq, dk, dbeta, dg, st);
-        default: return run_intra<TI, D, 2>(s, q, k, beta, g, t, list, b, dq, dk, dbeta, dg, st);
+        case 0: return run_intra<TI, D, 0>(s, q, k, beta, g, t, list, b, dq, dk, dbeta, dg, st, gd);
+        case 1: return run_intra<TI, D, 1>(s, q, k, beta, g, t, list, b, dq, dk, dbeta, dg, st, gd);
+        default: return run_intra<TI, D, 2>(s, q, k, beta, g, t, list, b, dq, dk, dbeta, dg, st, gd);
     }
 }
 
 }  // namespace
 
 cudaError_t launch_bwd_dstate(const Shape& s, int io_bf16, const void* dout, const void* v,
-                              const void* beta, Table t, Fwd f, Bwd b, void* dv, cudaStream_t st) {
+                              const void* beta, Table t, Fwd f, Bwd b, void* dv, cudaStream_t st, const Gdn2& gd) {
     if (s.K == 128)
-        return io_bf16 ? run_dstate<__nv_bfloat16, float, 128>(s, dout, v, beta, t, b.P, f.R, f.SIN, b.SBP, nullptr, b, dv, st)
-                       : run_dstate<float, float, 128>(s, dout, v, beta, t, b.P, f.R, f.SIN, b.SBP, nullptr, b, dv, st);
-    return io_bf16 ? run_dstate<__nv_bfloat16, float, 64>(s, dout, v, beta, t, b.P, f.R, f.SIN, b.SBP, nullptr, b, dv, st)
-                   : run_dstate<float, float, 64>(s, dout, v, beta, t, b.P, f.R, f.SIN, b.SBP, nullptr, b, dv, st);
+        return io_bf16 ? run_dstate<__nv_bfloat16, float, 128>(s, dout, v, beta, t, b.P, f.R, f.SIN, b.SBP, nullptr, b, dv, st, gd)
+                       : run_dstate<float, float, 128>(s, dout, v, beta, t, b.P, f.R, f.SIN, b.SBP, nullptr, b, dv, st, gd);
+    return io_bf16 ? run_dstate<__nv_bfloat16, float, 64>(s, dout, v, beta, t, b.P, f.R, f.SIN, b.SBP, nullptr, b, dv, st, gd)
+                   : run_dstate<float, float, 64>(s, dout, v, beta, t, b.P, f.R, f.SIN, b.SBP, nullptr, b, dv, st, gd);
 }
 
 cudaError_t launch_bwd_intra(const Shape& s, int io_bf16, int gate, const void* q, const void* k,
                              const void* beta, const float* g, Table t, Fwd f, Bwd b, void* dq,
-                             void* dk, void* dbeta, float* dg, cudaStream_t st) {
+                             void* dk, void* dbeta, float* dg, cudaStream_t st, const Gdn2& gd) {
     (void)f;
     if (s.K == 128)
-        return io_bf16 ? run_intra_gate<__nv_bfloat16, 128>(gate, s, q, k, beta, g, t, nullptr, b, dq, dk, dbeta, dg, st)
-                       : run_intra_gate<float, 128>(gate, s, q, k, beta, g, t, nullptr, b, dq, dk, dbeta, dg, st);
-    return io_bf16 ? run_intra_gate<__nv_bfloat16, 64>(gate, s, q, k, beta, g, t, nullptr, b, dq, dk, dbeta, dg, st)
-                   : run_intra_gate<float, 64>(gate, s, q, k, beta, g, t, nullptr, b, dq, dk, dbeta, dg, st);
+        return io_bf16 ? run_intra_gate<__nv_bfloat16, 128>(gate, s, q, k, beta, g, t, nullptr, b, dq, dk, dbeta, dg, st, gd)
+                       : run_intra_gate<float, 128>(gate, s, q, k, beta, g, t, nullptr, b, dq, dk, dbeta, dg, st, gd);
+    return io_bf16 ? run_intra_gate<__nv_bfloat16, 64>(gate, s, q, k, beta, g, t, nullptr, b, dq, dk, dbeta, dg, st, gd)
+                   : run_intra_gate<float, 64>(gate, s, q, k, beta, g, t, nullptr, b, dq, dk, dbeta, dg, st, gd);
 }
 
 cudaError_t launch_bwd_wide(const Shape& s, int gate, const void* q, const void* k, const void* v,

@@ -188,6 +188,17 @@ void set_last_error(const char* msg);
 // --------------------------------------------------------------- launchers
 // Each returns cudaSuccess or the launch error. Defined in the .cu files.
 cudaError_t launch_table(const Shape& s, int B, int T, const int32_t* cu, Table t, cudaStream_t st);
+// GatedDeltaNet-2 ("GatedDeltaNet-2 (NVlabs) — official spec transcription", §3):
+// an erase vector b per key channel and a write vector w per value channel take
+// beta's place (E = b .* K exp(G), Z = w .* V); erase NULL: the beta rule. The
+// CUDA-core chunk kernels take it; derase / dwrite receive the gradients.
+struct Gdn2 {
+    const void* erase = nullptr;   // [tokens, H, K] io dtype
+    const void* write = nullptr;   // [tokens, H, V] io dtype
+    void* derase = nullptr;
+    void* dwrite = nullptr;
+};
+
 // the optional input transforms (kda_prologue.cu): q, k normalised, decay activated
 struct PrologueArgs {
     const void *q, *k;                      // raw q, k (io dtype)
@@ -214,11 +225,11 @@ cudaError_t launch_epilogue(const Shape& s, int bf16, int gate, const EpilogueAr
 cudaError_t launch_recurrent(const Shape& s, int bf16, int gate, int T, const int32_t* cu, const void* q,
                              const void* k, const void* v, const void* beta, const float* g, const float* h0,
                              void* o, float* ht, int32_t* err, const float* A_log, const float* dt_bias,
-                             float lower_bound, int qk_norm, float eps, cudaStream_t st);
+                             float lower_bound, int qk_norm, float eps, cudaStream_t st, const Gdn2& gd = Gdn2{});
 
 cudaError_t launch_prep(const Shape& s, int io_bf16, int gate, const void* q, const void* k,
                         const void* v, const void* beta, const float* g, Table t, Fwd f,
-                        cudaStream_t st);
+                        cudaStream_t st, const Gdn2& gd = Gdn2{});
 
 // mode bit 0: write o; bit 1: write R and SIN for the backward pass.
 cudaError_t launch_fwd_scan(const Shape& s, int io_bf16, int mode, const float* h0, Table t,
@@ -252,11 +263,11 @@ cudaError_t launch_bwd_scan(const Shape& s, int io_bf16, const void* dout, const
 
 cudaError_t launch_bwd_dstate(const Shape& s, int io_bf16, const void* dout, const void* v,
                               const void* beta, Table t, Fwd f, Bwd b, void* dv,
-                              cudaStream_t st);
+                              cudaStream_t st, const Gdn2& gd = Gdn2{});
 
 cudaError_t launch_bwd_intra(const Shape& s, int io_bf16, int gate, const void* q,
                              const void* k, const void* beta, const float* g, Table t, Fwd f,
                              Bwd b, void* dq, void* dk, void* dbeta, float* dg,
-                             cudaStream_t st);
+                             cudaStream_t st, const Gdn2& gd = Gdn2{});
 
 }  // namespace kda

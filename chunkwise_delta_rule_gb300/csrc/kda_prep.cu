@@ -23,7 +23,7 @@ template <typename TI, int D, int GATE, bool TCOUT>
 __device__ __forceinline__ void prep_chunk(int c, int h, const Shape& s, const TI* __restrict__ q,
                                            const TI* __restrict__ k, const TI* __restrict__ v,
                                            const TI* __restrict__ beta, const float* __restrict__ g,
-                                           const Table& t, const Fwd& f, const FwdTC& ft) {
+                                           const Table& t, const Fwd& f, const FwdTC& ft, const Gdn2& gd) {
     constexpr int LD = D + 1;       // padded row stride of [BT x D] tiles
     constexpr int LA = BT + 1;      // padded row stride of [BT x BT] tiles
     extern __shared__ float smem[];
@@ -58,7 +58,12 @@ __device__ __forceinline__ void prep_chunk(int c, int h, const Shape& s, const T
         sQ[r * LD + col] = qv;
         sG[r * LD + col] = gv;
     }
-    if (tid < BT) sBeta[tid] = (tid < n) ? ld(beta + (size_t)(tok0 + tid) * H + h) : 0.f;
+    if (tid < BT) sBeta[tid] = (tid < n && !gd.erase) ? ld(beta + (size_t)(tok0 + tid) * H + h) : 0.f;
+    // GatedDeltaNet-2: the erase vector takes beta's place on the key rows of E
+    const TI* er = static_cast<const TI*>(gd.erase);
+    auto ebeta = [&](int r, int col) {
+        return er ? ((r < n) ? ld(er + ((size_t)(tok0 + r) * H + h) * D + col) : 0.f) : sBeta[r];
+    };
     __syncthreads();
     // ---- a1: inclusive cumsum down each feature column (padding rows keep G[n-1])
     if (tid < D) {
@@ -80,7 +85,7 @@ __device__ __forceinline__ void prep_chunk(int c, int h, const Shape& s, const T
             const int r = idx / D, col = idx % D;
             const int i = b * BC + (r & (BC - 1));
             const float e = exp2f(sG[i * LD + col] - sG[ra * LD + col]);
-            sL[r * LD + col] = (r < BC) ? sBeta[i] * sK[i * LD + col] * e : scale * sQ[i * LD + col] * e;
+            sL[r * LD + col] = (r < BC) ? ebeta(i, col) * sK[i * LD + col] * e : scale * sQ[i * LD + col] * e;
         }
         for (int idx = tid; idx < ncol * D; idx += NTHREADS) {
             const int j = idx / D, col = idx % D;
@@ -161,12 +166,14 @@ __device__ __forceinline__ void prep_chunk(int c, int h, const Shape& s, const T
     // E = diag(beta) K exp(G) into sR; beta*v into sQ
     for (int idx = tid; idx < BT * D; idx += NTHREADS) {
         const int r = idx / D, col = idx % D;
-        sR[r * LD + col] = sBeta[r] * sK[r * LD + col] * exp2f(sG[r * LD + col]);
+        sR[r * LD + col] = ebeta(r, col) * sK[r * LD + col] * exp2f(sG[r * LD + col]);
     }
     __syncthreads();  // all reads of sQ (queries) are done
     for (int idx = tid; idx < BT * D; idx += NTHREADS) {
         const int r = idx / D, col = idx % D;
-        sQ[r * LD + col] = (r < n) ? sBeta[r] * ld(v + ((size_t)(tok0 + r) * H + h) * D + col) : 0.f;
+        const size_t off = ((size_t)(tok0 + r) * H + h) * D + col;
+        const float wv = gd.write ? (r < n ? ld(static_cast<const TI*>(gd.write) + off) : 0.f) : sBeta[r];
+        sQ[r * LD + col] = (r < n) ? wv * ld(v + off) : 0.f;
     }
     __syncthreads();
     constexpr int TN = D / 32;
@@ -206,40 +213,40 @@ __device__ __forceinline__ void prep_chunk(int c, int h, const Shape& s, const T
 template <typename TI, int D, int GATE, bool TCOUT>
 __global__ void __launch_bounds__(NTHREADS, 1)
     k_prep(Shape s, const TI* __restrict__ q, const TI* __restrict__ k, const TI* __restrict__ v,
-           const TI* __restrict__ beta, const float* __restrict__ g, Table t, Fwd f, FwdTC ft) {
+           const TI* __restrict__ beta, const float* __restrict__ g, Table t, Fwd f, FwdTC ft, Gdn2 gd) {
     if (TCOUT) {
         const int cnt = ft.WLIST[0];
         for (int w = blockIdx.x; w < cnt; w += gridDim.x) {
             const int ch = ft.WLIST[1 + w];
-            prep_chunk<TI, D, GATE, TCOUT>(ch / s.H, ch % s.H, s, q, k, v, beta, g, t, f, ft);
+            prep_chunk<TI, D, GATE, TCOUT>(ch / s.H, ch % s.H, s, q, k, v, beta, g, t, f, ft, gd);
             __syncthreads();
         }
     } else {
-        prep_chunk<TI, D, GATE, TCOUT>(blockIdx.x, blockIdx.y, s, q, k, v, beta, g, t, f, ft);
+        prep_chunk<TI, D, GATE, TCOUT>(blockIdx.x, blockIdx.y, s, q, k, v, beta, g, t, f, ft, gd);
     }
 }
 
 template <typename TI, int D, int GATE, bool TCOUT>
 cudaError_t run(const Shape& s, const void* q, const void* k, const void* v, const void* beta,
-                const float* g, Table t, Fwd f, FwdTC ft, cudaStream_t st) {
+                const float* g, Table t, Fwd f, FwdTC ft, cudaStream_t st, const Gdn2& gd = Gdn2{}) {
     constexpr int LD = D + 1, LA = BT + 1;
     constexpr size_t smem = sizeof(float) * (3 * BT * LD + 2 * BC * LD + BT * LD + 2 * BT * LA + BT);
     auto kern = k_prep<TI, D, GATE, TCOUT>;
     cudaError_t e = set_smem_once<k_prep<TI, D, GATE, TCOUT>>(smem);
     if (e != cudaSuccess) return e;
     const dim3 grid = TCOUT ? dim3(sm_count()) : dim3(s.NC, s.H);
-    kern<<<grid, NTHREADS, smem, st>>>(s, (const TI*)q, (const TI*)k, (const TI*)v, (const TI*)beta, g, t, f, ft);
+    kern<<<grid, NTHREADS, smem, st>>>(s, (const TI*)q, (const TI*)k, (const TI*)v, (const TI*)beta, g, t, f, ft, gd);
     return cudaGetLastError();
 }
 
 template <typename TI, int D>
 cudaError_t run_gate(int gate, const Shape& s, const void* q, const void* k, const void* v,
-                     const void* beta, const float* g, Table t, Fwd f, cudaStream_t st) {
+                     const void* beta, const float* g, Table t, Fwd f, cudaStream_t st, const Gdn2& gd) {
     FwdTC none{};
     switch (gate) {
-        case 0: return run<TI, D, 0, false>(s, q, k, v, beta, g, t, f, none, st);
-        case 1: return run<TI, D, 1, false>(s, q, k, v, beta, g, t, f, none, st);
-        default: return run<TI, D, 2, false>(s, q, k, v, beta, g, t, f, none, st);
+        case 0: return run<TI, D, 0, false>(s, q, k, v, beta, g, t, f, none, st, gd);
+        case 1: return run<TI, D, 1, false>(s, q, k, v, beta, g, t, f, none, st, gd);
+        default: return run<TI, D, 2, false>(s, q, k, v, beta, g, t, f, none, st, gd);
     }
 }
 
@@ -257,13 +264,13 @@ cudaError_t launch_prep_wide(const Shape& s, int gate, const void* q, const void
 
 cudaError_t launch_prep(const Shape& s, int io_bf16, int gate, const void* q, const void* k,
                         const void* v, const void* beta, const float* g, Table t, Fwd f,
-                        cudaStream_t st) {
+                        cudaStream_t st, const Gdn2& gd) {
     if (s.K == 128) {
-        return io_bf16 ? run_gate<__nv_bfloat16, 128>(gate, s, q, k, v, beta, g, t, f, st)
-                       : run_gate<float, 128>(gate, s, q, k, v, beta, g, t, f, st);
+        return io_bf16 ? run_gate<__nv_bfloat16, 128>(gate, s, q, k, v, beta, g, t, f, st, gd)
+                       : run_gate<float, 128>(gate, s, q, k, v, beta, g, t, f, st, gd);
     }
-    return io_bf16 ? run_gate<__nv_bfloat16, 64>(gate, s, q, k, v, beta, g, t, f, st)
-                   : run_gate<float, 64>(gate, s, q, k, v, beta, g, t, f, st);
+    return io_bf16 ? run_gate<__nv_bfloat16, 64>(gate, s, q, k, v, beta, g, t, f, st, gd)
+                   : run_gate<float, 64>(gate, s, q, k, v, beta, g, t, f, st, gd);
 }
 
 }  // namespace kda

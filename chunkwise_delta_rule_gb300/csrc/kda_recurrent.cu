@@ -12,7 +12,8 @@
 // transcription", §3) runs per token on the loaded values: q and k divided by
 // sqrt(sum x^2 + eps) (every warp holds all keys, so a warp sum suffices), and
 // the decay -exp(A_log) softplus(g + dt_bias) or lower_bound sigmoid(exp(A_log)
-// (g + dt_bias)).
+// (g + dt_bias)). GatedDeltaNet-2 (same page, §3) erases along b .* k and writes
+// w .* v: r_t = w_t .* v_t - S~^T (b_t .* k_t).
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -33,6 +34,7 @@ struct RecIO {
     const float *A_log, *dt_bias;   // prologue: A_log NULL = g is the decay itself
     float lower_bound, eps;
     int qk_norm;
+    const void *erase, *write;      // GatedDeltaNet-2 vectors, or NULL (beta rule)
 };
 
 __device__ __forceinline__ float rwsum(float x) {
@@ -79,7 +81,7 @@ __device__ __forceinline__ float reduce8(const float (&x)[8], int lane) {
 // factor exp(g).
 template <typename TI, int KJ, int GATE>
 struct Tok {
-    float k[KJ], q[KJ], a[KJ], v, b;
+    float k[KJ], q[KJ], a[KJ], eb[KJ], v, b;
     __device__ __forceinline__ void load(const RecIO& io, size_t row, int K, int V, int col, int lane) {
         const TI* kp = static_cast<const TI*>(io.k) + row * K + lane;
         const TI* qp = static_cast<const TI*>(io.q) + row * K + lane;
@@ -95,7 +97,16 @@ struct Tok {
             a[0] = io.g[row];
         }
         v = ld(static_cast<const TI*>(io.v) + row * V + col);
-        b = ld(static_cast<const TI*>(io.beta) + row);
+        if (io.erase) {
+            const TI* ep = static_cast<const TI*>(io.erase) + row * K + lane;
+#pragma unroll
+            for (int j = 0; j < KJ; ++j) eb[j] = ld(ep + 32 * j);
+            b = ld(static_cast<const TI*>(io.write) + row * V + col);   // this column's write weight
+        } else {
+#pragma unroll
+            for (int j = 0; j < KJ; ++j) eb[j] = 1.f;
+            b = ld(static_cast<const TI*>(io.beta) + row);
+        }
     }
     __device__ __forceinline__ void finish(const RecIO& io, int h, int K, int lane, float scale) {
         float sq = scale, sk = 1.f;
@@ -186,11 +197,12 @@ __global__ void __launch_bounds__(RT) k_recurrent(Shape s, RecIO io) {
 #pragma unroll
             for (int j = 0; j < KJ; ++j) {
                 S[j][c] *= al[j];
-                acc = fmaf(S[j][c], cur.k[j], acc);
+                acc = fmaf(S[j][c], cur.k[j] * cur.eb[j], acc);
             }
             p[c] = acc;
         }
-        const float rm = cur.b * (cur.v - reduce8(p, lane));   // r_t of column cme
+        const float pm = reduce8(p, lane);
+        const float rm = io.erase ? cur.b * cur.v - pm : cur.b * (cur.v - pm);   // r_t of column cme
         // S = S~ + k r^T, then o = S^T (s q)
         float oq[8];
 #pragma unroll
@@ -237,9 +249,9 @@ cudaError_t run_recurrent_k(const Shape& s, int gate, const RecIO& io, cudaStrea
 cudaError_t launch_recurrent(const Shape& s, int bf16, int gate, int T, const int32_t* cu, const void* q,
                              const void* k, const void* v, const void* beta, const float* g, const float* h0,
                              void* o, float* ht, int32_t* err, const float* A_log, const float* dt_bias,
-                             float lower_bound, int qk_norm, float eps, cudaStream_t st) {
+                             float lower_bound, int qk_norm, float eps, cudaStream_t st, const Gdn2& gd) {
     if (s.V % RV != 0 || (s.K != 64 && s.K != 128)) return cudaErrorInvalidValue;
-    RecIO io{q, k, v, beta, g, h0, cu, o, ht, err, T, A_log, dt_bias, lower_bound, eps, qk_norm};
+    RecIO io{q, k, v, beta, g, h0, cu, o, ht, err, T, A_log, dt_bias, lower_bound, eps, qk_norm, gd.erase, gd.write};
     if (bf16) return s.K == 128 ? run_recurrent_k<__nv_bfloat16, 128>(s, gate, io, st)
                                 : run_recurrent_k<__nv_bfloat16, 64>(s, gate, io, st);
     return s.K == 128 ? run_recurrent_k<float, 128>(s, gate, io, st) : run_recurrent_k<float, 64>(s, gate, io, st);

@@ -43,6 +43,8 @@ class Problem:
     N: int
     A_log: Optional[torch.Tensor] = None
     dt_bias: Optional[torch.Tensor] = None
+    erase: Optional[torch.Tensor] = None
+    write: Optional[torch.Tensor] = None
 
     @property
     def state_shape(self):
@@ -58,20 +60,30 @@ def make_problem(q, k, v, g, beta, *, gate: str, scale: Optional[float] = None,
                  initial_state: Optional[torch.Tensor] = None,
                  cu_seqlens: Optional[torch.Tensor] = None, save_policy: int = 0,
                  A_log: Optional[torch.Tensor] = None, dt_bias: Optional[torch.Tensor] = None,
-                 lower_bound: float = 0.0, qk_l2norm: bool = False, l2norm_eps: float = 1e-6) -> Problem:
+                 lower_bound: float = 0.0, qk_l2norm: bool = False, l2norm_eps: float = 1e-6,
+                 erase: Optional[torch.Tensor] = None, write: Optional[torch.Tensor] = None) -> Problem:
     """Describe one call. With ``A_log`` (fp32 [H]) ``g`` is the raw gate and the
     decay is activated inside the operator (softplus form, or the lower-bound
     form when ``lower_bound`` < 0), with the optional ``dt_bias`` (fp32, [H, K]
     for a per-channel gate, [H] for a scalar one); ``qk_l2norm`` normalises q
-    and k per (token, head) first."""
+    and k per (token, head) first. GatedDeltaNet-2: ``erase`` [B, T, H, K] and
+    ``write`` [B, T, H, V] (the I/O dtype) replace ``beta``, which may be None."""
     _need(q.dim() == 4 and k.shape == q.shape, "q and k must be [B, T, H, K]")
     B, T, H, K = q.shape
     _need(v.dim() == 4 and v.shape[:3] == q.shape[:3], "v must be [B, T, H, V]")
     V = v.shape[3]
-    _need(q.dtype in _IO and k.dtype == q.dtype and v.dtype == q.dtype and beta.dtype == q.dtype,
+    _need((erase is None) == (write is None), "erase and write come together")
+    if erase is not None:
+        _need(erase.dtype == q.dtype and tuple(erase.shape) == (B, T, H, K), "erase must be [B, T, H, K], q's dtype")
+        _need(write.dtype == q.dtype and tuple(write.shape) == (B, T, H, V), "write must be [B, T, H, V], q's dtype")
+    else:
+        _need(beta is not None, "beta is required without erase/write")
+    _need(q.dtype in _IO and k.dtype == q.dtype and v.dtype == q.dtype and (beta is None or beta.dtype == q.dtype),
           "q, k, v, beta must share one dtype (bf16 or fp32)")
-    _need(tuple(beta.shape) == (B, T, H), "beta must be [B, T, H]")
-    for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta)):
+    _need(beta is None or tuple(beta.shape) == (B, T, H), "beta must be [B, T, H]")
+    for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta), ("erase", erase), ("write", write)):
+        if t is None:
+            continue
         _need(t.is_cuda and t.is_contiguous(), f"{name} must be a contiguous CUDA tensor")
     if gate == "none":
         _need(g is None, "g must be None without a gate")
@@ -95,7 +107,10 @@ def make_problem(q, k, v, g, beta, *, gate: str, scale: Optional[float] = None,
     c.io = _lib.DTYPES[_IO[q.dtype]]
     c.gate = _lib.GATES[gate]
     c.scale = float(scale) if scale is not None else 0.0
-    c.q, c.k, c.v, c.beta = q.data_ptr(), k.data_ptr(), v.data_ptr(), beta.data_ptr()
+    c.q, c.k, c.v = q.data_ptr(), k.data_ptr(), v.data_ptr()
+    c.beta = None if beta is None else beta.data_ptr()
+    c.erase = None if erase is None else erase.data_ptr()
+    c.write = None if write is None else write.data_ptr()
     c.g = None if g is None else g.data_ptr()
     c.h0 = None if initial_state is None else initial_state.data_ptr()
     c.save_policy = int(save_policy)
@@ -114,7 +129,7 @@ def make_problem(q, k, v, g, beta, *, gate: str, scale: Optional[float] = None,
     c.lower_bound = float(lower_bound)
     c.qk_l2norm = 1 if qk_l2norm else 0
     c.l2norm_eps = float(l2norm_eps)
-    return Problem(c, q, k, v, beta, g, initial_state, cu_seqlens, N, A_log, dt_bias)
+    return Problem(c, q, k, v, beta, g, initial_state, cu_seqlens, N, A_log, dt_bias, erase, write)
 
 
 def kda_workspace_size(p: Problem, for_backward: bool) -> int:
@@ -188,8 +203,9 @@ def kda_recurrent_fwd(p: Problem, *, output_final_state: bool = True, ht: Option
 def kda_chunk_bwd(p: Problem, do: torch.Tensor, dht: Optional[torch.Tensor] = None, *,
                   saved=None, workspace=None, stream=None, need_dh0: bool = True):
     """Backward pass of <do, o> + <dht, ht>. Returns dq, dk, dv, dg, dbeta, dh0,
-    and, when the problem activates its gate (A_log given), also dA_log and
-    ddt_bias (None without dt_bias)."""
+    then, when the problem activates its gate (A_log given), dA_log and
+    ddt_bias (None without dt_bias), then, with erase/write (GatedDeltaNet-2;
+    dbeta is None), derase and dwrite."""
     lib = _lib.load()
     dev = p.q.device
     _need(do.shape == p.v.shape and do.dtype == p.v.dtype and do.is_contiguous(), "do must match v")
@@ -199,7 +215,9 @@ def kda_chunk_bwd(p: Problem, do: torch.Tensor, dht: Optional[torch.Tensor] = No
     dq = torch.empty_like(p.q)
     dk = torch.empty_like(p.k)
     dv = torch.empty_like(p.v)
-    dbeta = torch.empty_like(p.beta)
+    dbeta = None if p.erase is not None else torch.empty_like(p.beta)
+    der = None if p.erase is None else torch.empty_like(p.erase)
+    dwr = None if p.write is None else torch.empty_like(p.write)
     dg = None if p.g is None else torch.empty_like(p.g)
     dh0 = torch.empty(p.state_shape, dtype=torch.float32, device=dev) if need_dh0 else None
     dA = None if p.A_log is None else torch.empty_like(p.A_log)
@@ -207,12 +225,16 @@ def kda_chunk_bwd(p: Problem, do: torch.Tensor, dht: Optional[torch.Tensor] = No
     ws = _buffer(kda_workspace_size(p, True), dev, workspace)
     nbytes = 0 if ws is None else ws.numel() * ws.element_size()
     st = lib.kda_chunk_bwd(ctypes.byref(p.c), _ptr(do), _ptr(dht), _ptr(saved), _ptr(dq), _ptr(dk),
-                           _ptr(dv), _ptr(dg), _ptr(dbeta), _ptr(dh0), _ptr(dA), _ptr(ddt), _ptr(ws), nbytes,
+                           _ptr(dv), _ptr(dg), _ptr(dbeta), _ptr(der), _ptr(dwr), _ptr(dh0), _ptr(dA), _ptr(ddt),
+                           _ptr(ws), nbytes,
                            _stream(stream))
     _lib.check(st, "kda_chunk_bwd")
+    out = (dq, dk, dv, dg, dbeta, dh0)
     if p.A_log is not None:
-        return dq, dk, dv, dg, dbeta, dh0, dA, ddt
-    return dq, dk, dv, dg, dbeta, dh0
+        out += (dA, ddt)
+    if p.erase is not None:
+        out += (der, dwr)
+    return out
 
 
 class ChunkKDAFunction(torch.autograd.Function):

@@ -93,6 +93,13 @@ typedef struct {
     int qk_l2norm;              /* 1: q and k are L2-normalised per (token, head) first:
                                    x / sqrt(sum x^2 + l2norm_eps) */
     float l2norm_eps;           /* <= 0 selects 1e-6 */
+    /* GatedDeltaNet-2 ("GatedDeltaNet-2 (NVlabs) — official spec transcription", §3): an erase
+     * vector per key channel and a write vector per value channel in place of beta,
+     *   r_t = write_t .* v_t - S~^T (erase_t .* k_t),  S_t = S~ + k_t r_t^T.
+     * Both NULL: the beta rule. Both set: beta is not read (may be NULL); the call runs on the
+     * fp32 CUDA-core chunk kernels at every width and I/O type. */
+    const void *erase;          /* [B*T, H, K] io dtype */
+    const void *write;          /* [B*T, H, V] io dtype */
 } kda_problem;
 
 /* Bytes of device workspace kda_chunk_fwd (for_backward = 0) or kda_chunk_bwd
@@ -123,11 +130,13 @@ kda_status kda_chunk_fwd(const kda_problem *p, void *o, float *ht, void *saved, 
  * dA_log [H] and ddt_bias (shaped like dt_bias) receive the parameters'
  * gradients (each may be NULL; ignored when its parameter is absent). The
  * parameter gradients are sums over tokens formed in a fixed order (no
- * atomics), so repeated calls agree bitwise. */
+ * atomics), so repeated calls agree bitwise. With erase/write (GatedDeltaNet-2)
+ * dbeta is not written (may be NULL) and derase [B*T, H, K], dwrite
+ * [B*T, H, V] (io dtype) receive their gradients; otherwise both are ignored. */
 kda_status kda_chunk_bwd(const kda_problem *p, const void *dout, const float *dht,
                          const void *saved, void *dq, void *dk, void *dv, float *dg,
-                         void *dbeta, float *dh0, float *dA_log, float *ddt_bias, void *ws,
-                         size_t ws_bytes, kda_stream_t stream);
+                         void *dbeta, void *derase, void *dwrite, float *dh0, float *dA_log,
+                         float *ddt_bias, void *ws, size_t ws_bytes, kda_stream_t stream);
 
 /* Forward pass for callers that cannot allocate device memory: code running
  * inside an allocator's own hooks, processes whose device memory is fully

@@ -97,7 +97,7 @@ def run_oracle_pairs(case, pairs, backward=True, nthreads=None):
 
 def run_oracle_prologue_arrays(q, k, v, beta, g_raw, *, A_log, dt_bias, lower_bound, eps, scale, gate,
                                seq_starts, h0=None, do=None, dht=None, backward=True, qk_norm=True,
-                               nthreads=None):
+                               nthreads=None, erase=None, write=None):
     """The operator with its prologue on, as a composition: q, k normalised
     per (token, head) (``qk_norm``), the decay activated from the raw gate
     (``A_log`` not None), then the recurrence; with ``backward`` the
@@ -108,7 +108,7 @@ def run_oracle_prologue_arrays(q, k, v, beta, g_raw, *, A_log, dt_bias, lower_bo
     kh = l2norm_fwd(k, eps)[0] if qk_norm else np.asarray(k, dtype=np.float64)
     g = g_raw if (A_log is None or g_raw is None) else gate_fwd(g_raw, A_log, dt_bias, lower_bound)
     res = run_recurrence(qh, kh, v, beta, g, seq_starts, gate=gate, scale=scale, h0=h0, do=do, dht=dht,
-                         backward=backward, nthreads=nthreads)
+                         backward=backward, nthreads=nthreads, erase=erase, write=write)
     if backward:
         if qk_norm:
             res["dq"] = l2norm_bwd(res["dq"], q, eps)

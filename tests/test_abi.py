@@ -24,7 +24,7 @@ def test_library_exports_every_declared_symbol():
     assert "kda_chunk_fwd" in names and "kda_chunk_bwd" in names
     for n in names:
         assert hasattr(lib, n), n
-    assert lib.kda_abi_version() == 2
+    assert lib.kda_abi_version() == 3
 
 
 def _prob(**kw):
@@ -124,7 +124,7 @@ def test_missing_pointers_and_workspace():
                              ctypes.c_void_p(0x10000), 100, None) == 3
     # backward: dg required with a gate
     z = ctypes.c_void_p(0x3000)
-    st = lib.kda_chunk_bwd(ctypes.byref(p), z, None, None, z, z, z, None, z, None, None, None, None, 0, None)
+    st = lib.kda_chunk_bwd(ctypes.byref(p), z, None, None, z, z, z, None, z, None, None, None, None, None, None, 0, None)
     assert st == 1 and "dg" in _lib.last_error()
 
 
