@@ -402,7 +402,7 @@ def run_ours(args):
                        "prologue": ("raw gate activated in the operator (softplus form, A_log, dt_bias) and "
                                     "q/k L2-normalised in the operator") if args.prologue else "off",
                        "rule": ("GatedDeltaNet-2: erase b = 2 sigmoid(N(0,1)) per key channel, write w = "
-                                "sigmoid(N(0,1)) per value channel (fp32 CUDA-core chunk kernels)") if args.gdn2
+                                "sigmoid(N(0,1)) per value channel") if args.gdn2
                        else "delta rule with beta",
                        "l2": "flushed by a 256 MiB write before every timed step"},
             "tflops": round(tflops, 2), "tflops_executed": round(tflops_exec, 2),

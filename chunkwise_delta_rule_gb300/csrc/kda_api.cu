@@ -70,7 +70,7 @@ struct Layout {
 
 // The tensor-core path serves bf16 I/O at K = V = 128; everything else runs
 // the fp32 CUDA-core kernels.
-bool use_tc(const kda_problem* p) { return p->io == KDA_BF16 && p->K == 128 && !p->erase; }
+bool use_tc(const kda_problem* p) { return p->io == KDA_BF16 && p->K == 128; }
 
 Layout layout(const Dims& d) {
     Layout L;
@@ -393,9 +393,9 @@ static kda_status chunk_fwd_core(const kda_problem* p, void* o, float* ht, void*
         } else {
             carve_fwd_tc(cw, d, f, false);
         }
-        e = traced("k_prep_tc", cs, [&] { return kda::launch_prep_tc(s, (int)p->gate, save ? 1 : 0, p->q, p->k, p->v, p->beta, p->g, t, f, cs); });
+        e = traced("k_prep_tc", cs, [&] { return kda::launch_prep_tc(s, (int)p->gate, save ? 1 : 0, p->q, p->k, p->v, p->beta, p->g, t, f, cs, kda::Gdn2{p->erase, p->write}); });
         if (e != cudaSuccess) return cuda_fail(e, "prep");
-        e = traced("k_prep_wide", cs, [&] { return kda::launch_prep_wide(s, (int)p->gate, p->q, p->k, p->v, p->beta, p->g, t, f, cs); });
+        e = traced("k_prep_wide", cs, [&] { return kda::launch_prep_wide(s, (int)p->gate, p->q, p->k, p->v, p->beta, p->g, t, f, cs, kda::Gdn2{p->erase, p->write}); });
         if (e != cudaSuccess) return cuda_fail(e, "prep (wide chunks)");
         // policy A: outputs and saved S, R from one scan, or (when the SMs allow) the output
         // scan and the S, R scan side by side
@@ -475,9 +475,9 @@ static kda_status chunk_bwd_core(const kda_problem* p, const void* dout, const f
         if (e != cudaSuccess) return cuda_fail(e, "chunk table");
         Side* sd = nullptr;
         if (!save) {
-            e = traced("k_prep_tc", cs, [&] { return kda::launch_prep_tc(s, gate, 1, p->q, p->k, p->v, p->beta, p->g, t, f, cs); });
+            e = traced("k_prep_tc", cs, [&] { return kda::launch_prep_tc(s, gate, 1, p->q, p->k, p->v, p->beta, p->g, t, f, cs, kda::Gdn2{p->erase, p->write}); });
             if (e != cudaSuccess) return cuda_fail(e, "prep (recompute)");
-            e = traced("k_prep_wide", cs, [&] { return kda::launch_prep_wide(s, gate, p->q, p->k, p->v, p->beta, p->g, t, f, cs); });
+            e = traced("k_prep_wide", cs, [&] { return kda::launch_prep_wide(s, gate, p->q, p->k, p->v, p->beta, p->g, t, f, cs, kda::Gdn2{p->erase, p->write}); });
             if (e != cudaSuccess) return cuda_fail(e, "prep (recompute, wide chunks)");
             // the S, R recompute and the reverse scan need only the prep: side by side
             sd = side_stream();
@@ -492,10 +492,10 @@ static kda_status chunk_bwd_core(const kda_problem* p, const void* dout, const f
         e = traced("k_bwd_scan_tc", cs, [&] { return kda::launch_bwd_scan_tc(s, dout, dht, t, f, b, dh0, cs); });
         if (e != cudaSuccess) return cuda_fail(e, "reverse scan");
         if (sd && (e = side_join(sd, cs)) != cudaSuccess) return cuda_fail(e, "side stream");
-        e = traced("k_bwd_consumer_tc", cs, [&] { return kda::launch_bwd_consumer_tc(s, gate, p->q, p->k, p->v, p->beta, p->g, dout, t, f, b, dq, dk, dv, dbeta, dg, cs); });
+        e = traced("k_bwd_consumer_tc", cs, [&] { return kda::launch_bwd_consumer_tc(s, gate, p->q, p->k, p->v, p->beta, p->g, dout, t, f, b, dq, dk, dv, dbeta, dg, cs, gd); });
         if (e != cudaSuccess) return cuda_fail(e, "consumer");
         if (gate != KDA_GATE_NONE) {
-            e = traced("k_bwd_wide", cs, [&] { return kda::launch_bwd_wide(s, gate, p->q, p->k, p->v, p->beta, p->g, dout, t, f, b, scr, dq, dk, dv, dbeta, dg, cs); });
+            e = traced("k_bwd_wide", cs, [&] { return kda::launch_bwd_wide(s, gate, p->q, p->k, p->v, p->beta, p->g, dout, t, f, b, scr, dq, dk, dv, dbeta, dg, cs, gd); });
             if (e != cudaSuccess) return cuda_fail(e, "consumer (wide chunks)");
         }
         return KDA_OK;

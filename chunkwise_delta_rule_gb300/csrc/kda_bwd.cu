@@ -580,11 +580,11 @@ cudaError_t launch_bwd_intra(const Shape& s, int io_bf16, int gate, const void* 
 cudaError_t launch_bwd_wide(const Shape& s, int gate, const void* q, const void* k, const void* v,
                             const void* beta, const float* g, const void* dout, Table t, FwdTC f,
                             BwdTC bt, Bwd scratch, void* dq, void* dk, void* dv, void* dbeta, float* dg,
-                            cudaStream_t st) {
+                            cudaStream_t st, const Gdn2& gd) {
     cudaError_t e = run_dstate<__nv_bfloat16, __nv_bfloat16, 128>(s, dout, v, beta, t, bt.P, f.R, f.HS, bt.SBP,
-                                                                  f.WLIST, scratch, dv, st);
+                                                                  f.WLIST, scratch, dv, st, gd);
     if (e != cudaSuccess) return e;
-    return run_intra_gate<__nv_bfloat16, 128>(gate, s, q, k, beta, g, t, f.WLIST, scratch, dq, dk, dbeta, dg, st);
+    return run_intra_gate<__nv_bfloat16, 128>(gate, s, q, k, beta, g, t, f.WLIST, scratch, dq, dk, dbeta, dg, st, gd);
 }
 
 }  // namespace kda

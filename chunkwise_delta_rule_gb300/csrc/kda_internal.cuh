@@ -190,8 +190,8 @@ void set_last_error(const char* msg);
 cudaError_t launch_table(const Shape& s, int B, int T, const int32_t* cu, Table t, cudaStream_t st);
 // GatedDeltaNet-2 ("GatedDeltaNet-2 (NVlabs) — official spec transcription", §3):
 // an erase vector b per key channel and a write vector w per value channel take
-// beta's place (E = b .* K exp(G), Z = w .* V); erase NULL: the beta rule. The
-// CUDA-core chunk kernels take it; derase / dwrite receive the gradients.
+// beta's place (E = b .* K exp(G), Z = w .* V); erase NULL: the beta rule. Every
+// chunk kernel that reads beta takes it; derase / dwrite receive the gradients.
 struct Gdn2 {
     const void* erase = nullptr;   // [tokens, H, K] io dtype
     const void* write = nullptr;   // [tokens, H, V] io dtype
@@ -238,10 +238,11 @@ cudaError_t launch_fwd_scan(const Shape& s, int io_bf16, int mode, const float* 
 // Tensor-core path (bf16 I/O, K = V = 128).
 cudaError_t launch_prep_tc(const Shape& s, int gate, int for_bwd, const void* q, const void* k,
                            const void* v, const void* beta, const float* g, Table t, FwdTC f,
-                           cudaStream_t st);
+                           cudaStream_t st, const Gdn2& gd = Gdn2{});
 // CUDA-core prep of the chunks flagged WIDE, written in the tensor-core layouts.
 cudaError_t launch_prep_wide(const Shape& s, int gate, const void* q, const void* k, const void* v,
-                             const void* beta, const float* g, Table t, FwdTC ft, cudaStream_t st);
+                             const void* beta, const float* g, Table t, FwdTC ft, cudaStream_t st,
+                             const Gdn2& gd = Gdn2{});
 cudaError_t launch_fwd_scan_tc(const Shape& s, int mode, const float* h0, Table t, FwdTC f, void* o,
                                float* ht, cudaStream_t st);
 
@@ -250,13 +251,13 @@ cudaError_t launch_bwd_scan_tc(const Shape& s, const void* dout, const float* dh
 cudaError_t launch_bwd_consumer_tc(const Shape& s, int gate, const void* q, const void* k, const void* v,
                                    const void* beta, const float* g, const void* dout, Table t, FwdTC f,
                                    BwdTC b, void* dq, void* dk, void* dv, void* dbeta, float* dg,
-                                   cudaStream_t st);
+                                   cudaStream_t st, const Gdn2& gd = Gdn2{});
 // CUDA-core consumers for the WIDE chunks of the tensor-core path (reading its
 // bf16 intermediates, fp32 scratch in `scratch`).
 cudaError_t launch_bwd_wide(const Shape& s, int gate, const void* q, const void* k, const void* v,
                             const void* beta, const float* g, const void* dout, Table t, FwdTC f,
                             BwdTC b, Bwd scratch, void* dq, void* dk, void* dv, void* dbeta, float* dg,
-                            cudaStream_t st);
+                            cudaStream_t st, const Gdn2& gd = Gdn2{});
 
 cudaError_t launch_bwd_scan(const Shape& s, int io_bf16, const void* dout, const float* dht,
                             Table t, Fwd f, Bwd b, float* dh0, cudaStream_t st);

@@ -253,12 +253,13 @@ cudaError_t run_gate(int gate, const Shape& s, const void* q, const void* k, con
 }  // namespace
 
 cudaError_t launch_prep_wide(const Shape& s, int gate, const void* q, const void* k, const void* v,
-                             const void* beta, const float* g, Table t, FwdTC ft, cudaStream_t st) {
+                             const void* beta, const float* g, Table t, FwdTC ft, cudaStream_t st,
+                             const Gdn2& gd) {
     Fwd none{};
     switch (gate) {
-        case 0: return run<__nv_bfloat16, 128, 0, true>(s, q, k, v, beta, g, t, none, ft, st);
-        case 1: return run<__nv_bfloat16, 128, 1, true>(s, q, k, v, beta, g, t, none, ft, st);
-        default: return run<__nv_bfloat16, 128, 2, true>(s, q, k, v, beta, g, t, none, ft, st);
+        case 0: return run<__nv_bfloat16, 128, 0, true>(s, q, k, v, beta, g, t, none, ft, st, gd);
+        case 1: return run<__nv_bfloat16, 128, 1, true>(s, q, k, v, beta, g, t, none, ft, st, gd);
+        default: return run<__nv_bfloat16, 128, 2, true>(s, q, k, v, beta, g, t, none, ft, st, gd);
     }
 }
 

@@ -446,7 +446,7 @@ __global__ void __launch_bounds__(CT, 1)
                       const __grid_constant__ CUtensorMap tmv, const bf16* __restrict__ beta,
                       const float* __restrict__ g, Table t, FwdTC f, BwdTC bw, bf16* __restrict__ dq,
                       bf16* __restrict__ dk, bf16* __restrict__ dv, bf16* __restrict__ dbeta,
-                      float* __restrict__ dg) {
+                      float* __restrict__ dg, Gdn2 gd) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                            ~static_cast<uintptr_t>(1023));
@@ -523,7 +523,8 @@ __global__ void __launch_bounds__(CT, 1)
             }
         }
         const float beta_r =
-            (k == 0) ? ((tid < BT && tid < n) ? bfx(beta + (size_t)(tok0 + tid) * H + h) : 0.f) : __bfloat162float(beta_nx);
+            (k == 0) ? ((tid < BT && tid < n && !gd.erase) ? bfx(beta + (size_t)(tok0 + tid) * H + h) : 0.f)
+                     : __bfloat162float(beta_nx);
         // the G tile for a scalar gate (or zeros): tile C_A is free since the previous unit's F2
         if (GATE != 2) {
             for (int idx = tid; idx < BT * D / 4; idx += CT) {
@@ -630,13 +631,26 @@ __global__ void __launch_bounds__(CT, 1)
                 const uint4 vv = *reinterpret_cast<const uint4*>(base + X_V + tc::sw128_off(BT, r, cc * 16));
                 const bf16* pp2 = reinterpret_cast<const bf16*>(&pp);
                 const bf16* vv2 = reinterpret_cast<const bf16*>(&vv);
-                uint32_t out[4];
+                uint32_t out[4], wout[4];
+                if (gd.write) {   // GatedDeltaNet-2: dv = w .* P, dw = v .* P
+                    const uint4 ww = *reinterpret_cast<const uint4*>(static_cast<const bf16*>(gd.write) + tok * D + cc * 8);
+                    const bf16* ww2 = reinterpret_cast<const bf16*>(&ww);
 #pragma unroll
-                for (int e = 0; e < 8; e += 2) {
-                    const float p0 = __bfloat162float(pp2[e]), p1 = __bfloat162float(pp2[e + 1]);
-                    acc = fmaf(__bfloat162float(vv2[e]), p0, acc);
-                    acc = fmaf(__bfloat162float(vv2[e + 1]), p1, acc);
-                    out[e / 2] = tc::pack_bf16(bt * p0, bt * p1);
+                    for (int e = 0; e < 8; e += 2) {
+                        const float p0 = __bfloat162float(pp2[e]), p1 = __bfloat162float(pp2[e + 1]);
+                        out[e / 2] = tc::pack_bf16(__bfloat162float(ww2[e]) * p0, __bfloat162float(ww2[e + 1]) * p1);
+                        wout[e / 2] = tc::pack_bf16(__bfloat162float(vv2[e]) * p0, __bfloat162float(vv2[e + 1]) * p1);
+                    }
+                    *reinterpret_cast<uint4*>(static_cast<bf16*>(gd.dwrite) + tok * D + cc * 8) =
+                        make_uint4(wout[0], wout[1], wout[2], wout[3]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; e += 2) {
+                        const float p0 = __bfloat162float(pp2[e]), p1 = __bfloat162float(pp2[e + 1]);
+                        acc = fmaf(__bfloat162float(vv2[e]), p0, acc);
+                        acc = fmaf(__bfloat162float(vv2[e + 1]), p1, acc);
+                        out[e / 2] = tc::pack_bf16(bt * p0, bt * p1);
+                    }
                 }
                 *reinterpret_cast<uint4*>(dv + tok * D + cc * 8) = make_uint4(out[0], out[1], out[2], out[3]);
             }
@@ -689,7 +703,10 @@ __global__ void __launch_bounds__(CT, 1)
                     const float al = (GATE == 2) ? sA[aidx(j, kr)] : 1.f;
                     const bool in = j < n;
                     kz[e] = in ? ((GATE == 2) ? kv * tc::rcp_approx(al) : kv) : 0.f;
-                    ea[e] = in ? sBeta[j] * kv * al : 0.f;
+                    const float eb = gd.erase ? (in ? bfx(static_cast<const bf16*>(gd.erase) +
+                                                          ((size_t)(tok0 + j) * H + h) * D + kr) : 0.f)
+                                              : sBeta[j];
+                    ea[e] = in ? eb * kv * al : 0.f;
                     qa[e] = in ? scale * qv * al : 0.f;
                 }
                 *reinterpret_cast<float4*>(base + X_KZ + tc::sw128_off(D, kr, gq * 16)) = make_float4(kz[0], kz[1], kz[2], kz[3]);
@@ -758,6 +775,16 @@ __global__ void __launch_bounds__(CT, 1)
 #pragma unroll
             for (int cb = 0; cb < 32; cb += 16) {
                 float tq[16], tp[16];
+                // GatedDeltaNet-2 key rows: the erase vector on columns cb0+cb.. of token i
+                uint4 eb4[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+                if (gd.erase && !isQ && i < n) {
+                    const uint4* ep = reinterpret_cast<const uint4*>(static_cast<const bf16*>(gd.erase) +
+                                                                     ((size_t)(tok0 + i) * H + h) * D + cb0 + cb);
+                    eb4[0] = ep[0];
+                    eb4[1] = ep[1];
+                }
+                const bf16* ebv = reinterpret_cast<const bf16*>(eb4);
+                uint32_t dbw[8];
                 const uint32_t tqa = tc::taddr(tb + 256, 32 * quad, cb0 + cb);
                 tc::tmem_ld16(tqa, tq);
                 tc::tmem_ld16(tc::taddr(tb + 64, 32 * quad, cb0 + cb), tp);
@@ -776,10 +803,21 @@ __global__ void __launch_bounds__(CT, 1)
                     } else {
                         const float Et = fac * tq[jj] - gam * tp[jj];               // gamma * E_bar
                         const float kv = xq;
-                        sDK[i * LG + kr] = bt * Et;
-                        tq[jj] = bt * kv * Et;                                      // erase part of G_bar
+                        const float be = gd.erase ? __bfloat162float(ebv[jj]) : bt;
+                        sDK[i * LG + kr] = be * Et;
+                        tq[jj] = be * kv * Et;                                      // erase part of G_bar
                         part = fmaf(kv, Et, part);
+                        if (gd.erase) {   // db = K gamma .* E_bar, packed in pairs (tp[jj] is spent)
+                            if (jj & 1) dbw[jj / 2] = tc::pack_bf16(tp[jj - 1], kv * Et);
+                            else tp[jj] = kv * Et;
+                        }
                     }
+                }
+                if (gd.erase && !isQ && i < n) {
+                    uint4* dst = reinterpret_cast<uint4*>(static_cast<bf16*>(gd.derase) +
+                                                          ((size_t)(tok0 + i) * H + h) * D + cb0 + cb);
+                    dst[0] = make_uint4(dbw[0], dbw[1], dbw[2], dbw[3]);
+                    dst[1] = make_uint4(dbw[4], dbw[5], dbw[6], dbw[7]);
                 }
                 if (isQ) {
 #pragma unroll
@@ -837,7 +875,8 @@ __global__ void __launch_bounds__(CT, 1)
                     ++nC;
                 }
                 // kept as bf16 so the load stays in flight until the next unit starts
-                if (tid < BT) beta_nx = (tid < nm[1]) ? beta[(size_t)(nm[2] + tid) * H + nh] : __float2bfloat16_rn(0.f);
+                if (tid < BT)
+                    beta_nx = (tid < nm[1] && !gd.erase) ? beta[(size_t)(nm[2] + tid) * H + nh] : __float2bfloat16_rn(0.f);
             }
         }
         // ---- F3: dk, dbeta; key rows add the erase part of G_bar; the endpoint terms of the last
@@ -852,7 +891,7 @@ __global__ void __launch_bounds__(CT, 1)
                 *reinterpret_cast<uint4*>(dk + ((size_t)(tok0 + r) * H + h) * D + cc * 8) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
             }
         }
-        if (tid < BT && tid < n)
+        if (tid < BT && tid < n && !gd.erase)
             dbeta[(size_t)(tok0 + tid) * H + h] = __float2bfloat16_rn(sRowP[tid] + sRowP[BT + tid] + sRowP[2 * BT + tid] +
                                                                       sRowP[3 * BT + tid] + sDbw[tid]);
         if (GATE != 0) {
@@ -938,7 +977,7 @@ __global__ void __launch_bounds__(CT, 1)
 template <int GATE>
 cudaError_t run_consumer(const Shape& s, const void* q, const void* k, const void* v, const void* beta,
                          const float* g, const void* dout, Table t, FwdTC f, BwdTC b, void* dq, void* dk,
-                         void* dv, void* dbeta, float* dg, cudaStream_t st) {
+                         void* dv, void* dbeta, float* dg, cudaStream_t st, const Gdn2& gd) {
     cudaError_t e = set_smem_once<k_bwd_consumer_tc<GATE>>(CONS_SMEM);
     if (e != cudaSuccess) return e;
     CUtensorMap mq, mk, mo, mg, mv;
@@ -951,7 +990,7 @@ cudaError_t run_consumer(const Shape& s, const void* q, const void* k, const voi
     if (units <= 0) return cudaSuccess;
     const int grid = (int)(units < sm_count() ? units : sm_count());   // one CTA per SM, persistent
     k_bwd_consumer_tc<GATE><<<grid, CT, CONS_SMEM, st>>>(s, mq, mk, mo, mg, mv, (const bf16*)beta, g, t, f, b,
-                                                         (bf16*)dq, (bf16*)dk, (bf16*)dv, (bf16*)dbeta, dg);
+                                                         (bf16*)dq, (bf16*)dk, (bf16*)dv, (bf16*)dbeta, dg, gd);
     return cudaGetLastError();
 }
 
@@ -971,11 +1010,11 @@ cudaError_t launch_bwd_scan_tc(const Shape& s, const void* dout, const float* dh
 cudaError_t launch_bwd_consumer_tc(const Shape& s, int gate, const void* q, const void* k, const void* v,
                                    const void* beta, const float* g, const void* dout, Table t, FwdTC f,
                                    BwdTC b, void* dq, void* dk, void* dv, void* dbeta, float* dg,
-                                   cudaStream_t st) {
+                                   cudaStream_t st, const Gdn2& gd) {
     switch (gate) {
-        case 0: return run_consumer<0>(s, q, k, v, beta, g, dout, t, f, b, dq, dk, dv, dbeta, dg, st);
-        case 1: return run_consumer<1>(s, q, k, v, beta, g, dout, t, f, b, dq, dk, dv, dbeta, dg, st);
-        default: return run_consumer<2>(s, q, k, v, beta, g, dout, t, f, b, dq, dk, dv, dbeta, dg, st);
+        case 0: return run_consumer<0>(s, q, k, v, beta, g, dout, t, f, b, dq, dk, dv, dbeta, dg, st, gd);
+        case 1: return run_consumer<1>(s, q, k, v, beta, g, dout, t, f, b, dq, dk, dv, dbeta, dg, st, gd);
+        default: return run_consumer<2>(s, q, k, v, beta, g, dout, t, f, b, dq, dk, dv, dbeta, dg, st, gd);
     }
 }
 

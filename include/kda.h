@@ -96,8 +96,8 @@ typedef struct {
     /* GatedDeltaNet-2 ("GatedDeltaNet-2 (NVlabs) — official spec transcription", §3): an erase
      * vector per key channel and a write vector per value channel in place of beta,
      *   r_t = write_t .* v_t - S~^T (erase_t .* k_t),  S_t = S~ + k_t r_t^T.
-     * Both NULL: the beta rule. Both set: beta is not read (may be NULL); the call runs on the
-     * fp32 CUDA-core chunk kernels at every width and I/O type. */
+     * Both NULL: the beta rule. Both set: beta is not read (may be NULL); every path takes
+     * them (tensor-core, CUDA-core, token-by-token). */
     const void *erase;          /* [B*T, H, K] io dtype */
     const void *write;          /* [B*T, H, V] io dtype */
 } kda_problem;
