@@ -44,6 +44,7 @@ class KdaProblem(ctypes.Structure):
         ("l2norm_eps", ctypes.c_float),
         ("erase", ctypes.c_void_p),
         ("write", ctypes.c_void_p),
+        ("HV", ctypes.c_int),
     ]
 
 

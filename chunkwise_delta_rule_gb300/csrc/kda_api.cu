@@ -37,6 +37,8 @@ kda_status check_dims(const kda_problem* p, Dims& d) {
     if (p->save_policy != 0 && p->save_policy != 1)
         return fail(KDA_ERR_INVALID_ARG, "save_policy must be 0 or 1");
     if (p->qk_l2norm != 0 && p->qk_l2norm != 1) return fail(KDA_ERR_INVALID_ARG, "qk_l2norm must be 0 or 1");
+    if (p->HV != 0 && p->HV != p->H && (p->HV < p->H || p->HV % p->H != 0 || p->HV > 65535))
+        return fail(KDA_ERR_INVALID_ARG, "HV must be 0 or a multiple of H (at most 65535)");
     if ((p->erase == nullptr) != (p->write == nullptr))
         return fail(KDA_ERR_INVALID_ARG, "erase and write come together (GatedDeltaNet-2)");
     if (p->A_log && p->gate == KDA_GATE_NONE) return fail(KDA_ERR_INVALID_ARG, "A_log needs a gate");
@@ -187,6 +189,22 @@ kda::Shape shape_of(const kda_problem* p, const Dims& d) {
     return s;
 }
 
+// Grouped value heads: the problem the rest of the library sees has one key head per value
+// head (q, k expanded in the workspace).
+bool gva(const kda_problem* p) { return p->HV != 0 && p->HV != p->H; }
+kda_problem gva_inner(const kda_problem* p, const void* qx, const void* kx) {
+    kda_problem c = *p;
+    c.H = p->HV;
+    c.HV = 0;
+    c.q = qx;
+    c.k = kx;
+    return c;
+}
+size_t gva_bytes(const kda_problem* p, const Dims& d, bool bwd) {
+    const size_t one = up((size_t)(p->io == KDA_BF16 ? 2 : 4) * d.Ttot * p->HV * d.D);
+    return one * (bwd ? 4 : 2);   // q, k copies (and, backward, their gradients)
+}
+
 // The optional prologue (normalised q, k; activated decay) and what it needs.
 bool has_prologue(const kda_problem* p) { return p->A_log || p->qk_l2norm; }
 float l2eps(const kda_problem* p) { return p->l2norm_eps > 0.f ? p->l2norm_eps : 1e-6f; }
@@ -328,7 +346,7 @@ void set_last_error(const char* msg) { g_err = msg; }
 
 extern "C" {
 
-int kda_abi_version(void) { return 3; }
+int kda_abi_version(void) { return 4; }
 
 const char* kda_last_error(void) { return g_err.c_str(); }
 
@@ -346,6 +364,10 @@ size_t kda_workspace_size(const kda_problem* p, int for_backward) {
     Dims d;
     if (check_dims(p, d) != KDA_OK) return 0;
     if (d.Ttot == 0) return 0;
+    if (gva(p)) {
+        const kda_problem in = gva_inner(p, p->q, p->k);
+        return kda_workspace_size(&in, for_backward) + gva_bytes(p, d, for_backward != 0);
+    }
     const kda_problem c = core_problem(p);
     return core_workspace(&c, d, for_backward) + prologue_bytes(p, d, for_backward != 0);
 }
@@ -353,6 +375,10 @@ size_t kda_workspace_size(const kda_problem* p, int for_backward) {
 size_t kda_saved_size(const kda_problem* p) {
     Dims d;
     if (check_dims(p, d) != KDA_OK) return 0;
+    if (gva(p)) {
+        const kda_problem in = gva_inner(p, p->q, p->k);
+        return kda_saved_size(&in);
+    }
     if (!p->save_policy || d.Ttot == 0) return 0;
     const Layout L = layout(d);
     return use_tc(p) ? L.ftc + L.ftc_b : L.fcore + L.fextra;
@@ -557,8 +583,8 @@ static kda_status run_prologue(const kda_problem* p, const Dims& d, char* w, kda
     return e == cudaSuccess ? KDA_OK : cuda_fail(e, "prologue");
 }
 
-kda_status kda_chunk_fwd(const kda_problem* p, void* o, float* ht, void* saved, void* ws, size_t ws_bytes,
-                         kda_stream_t stream) {
+static kda_status chunk_fwd_pro(const kda_problem* p, void* o, float* ht, void* saved, void* ws, size_t ws_bytes,
+                                kda_stream_t stream) {
     if (!p || !has_prologue(p)) return chunk_fwd_core(p, o, ht, saved, ws, ws_bytes, stream);
     Dims d;
     kda_status st = check_dims(p, d);
@@ -573,9 +599,9 @@ kda_status kda_chunk_fwd(const kda_problem* p, void* o, float* ht, void* saved, 
     return chunk_fwd_core(&c, o, ht, saved, ws, core, stream);
 }
 
-kda_status kda_chunk_bwd(const kda_problem* p, const void* dout, const float* dht, const void* saved, void* dq,
-                         void* dk, void* dv, float* dg, void* dbeta, void* derase, void* dwrite, float* dh0,
-                         float* dA_log, float* ddt_bias, void* ws, size_t ws_bytes, kda_stream_t stream) {
+static kda_status chunk_bwd_pro(const kda_problem* p, const void* dout, const float* dht, const void* saved, void* dq,
+                                void* dk, void* dv, float* dg, void* dbeta, void* derase, void* dwrite, float* dh0,
+                                float* dA_log, float* ddt_bias, void* ws, size_t ws_bytes, kda_stream_t stream) {
     if (!p || !has_prologue(p))
         return chunk_bwd_core(p, dout, dht, saved, dq, dk, dv, dg, dbeta, derase, dwrite, dh0, ws, ws_bytes, stream);
     Dims d;
@@ -632,6 +658,66 @@ kda_status kda_chunk_bwd(const kda_problem* p, const void* dout, const float* dh
     return e == cudaSuccess ? KDA_OK : cuda_fail(e, "epilogue");
 }
 
+// Grouped value heads: q, k copied per value head after the pipeline's workspace, then the
+// one-key-head-per-value-head problem.
+static kda_status gva_expand(const kda_problem* p, const Dims& d, char* w, kda_problem& in, cudaStream_t cs) {
+    const size_t one = up((size_t)(p->io == KDA_BF16 ? 2 : 4) * d.Ttot * p->HV * d.D);
+    in = gva_inner(p, w, w + one);
+    cudaError_t e = traced("k_gva_expand", cs, [&] {
+        return kda::launch_gva_expand(d.Ttot, p->HV, p->HV / p->H, d.D, p->io == KDA_BF16, p->q, p->k,
+                                      const_cast<void*>(in.q), const_cast<void*>(in.k), cs);
+    });
+    return e == cudaSuccess ? KDA_OK : cuda_fail(e, "grouped heads: expand q, k");
+}
+
+kda_status kda_chunk_fwd(const kda_problem* p, void* o, float* ht, void* saved, void* ws, size_t ws_bytes,
+                         kda_stream_t stream) {
+    if (!p || !gva(p)) return chunk_fwd_pro(p, o, ht, saved, ws, ws_bytes, stream);
+    Dims d;
+    kda_status st = check_dims(p, d);
+    if (st != KDA_OK) return st;
+    if ((st = check_inputs(p, d)) != KDA_OK) return st;
+    kda_problem in = gva_inner(p, p->q, p->k);
+    if (d.Ttot == 0) return chunk_fwd_pro(&in, o, ht, saved, ws, ws_bytes, stream);
+    const size_t core = kda_workspace_size(&in, 0);
+    if ((st = check_ws(ws, ws_bytes, core + gva_bytes(p, d, false))) != KDA_OK) return st;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    if ((st = gva_expand(p, d, static_cast<char*>(ws) + core, in, cs)) != KDA_OK) return st;
+    return chunk_fwd_pro(&in, o, ht, saved, ws, core, stream);
+}
+
+kda_status kda_chunk_bwd(const kda_problem* p, const void* dout, const float* dht, const void* saved, void* dq,
+                         void* dk, void* dv, float* dg, void* dbeta, void* derase, void* dwrite, float* dh0,
+                         float* dA_log, float* ddt_bias, void* ws, size_t ws_bytes, kda_stream_t stream) {
+    if (!p || !gva(p))
+        return chunk_bwd_pro(p, dout, dht, saved, dq, dk, dv, dg, dbeta, derase, dwrite, dh0, dA_log, ddt_bias, ws,
+                             ws_bytes, stream);
+    Dims d;
+    kda_status st = check_dims(p, d);
+    if (st != KDA_OK) return st;
+    if ((st = check_inputs(p, d)) != KDA_OK) return st;
+    kda_problem in = gva_inner(p, p->q, p->k);
+    if (d.Ttot == 0)
+        return chunk_bwd_pro(&in, dout, dht, saved, dq, dk, dv, dg, dbeta, derase, dwrite, dh0, dA_log, ddt_bias, ws,
+                             ws_bytes, stream);
+    if (!dq || !dk) return fail(KDA_ERR_INVALID_ARG, "dq and dk must be non-NULL");
+    const size_t core = kda_workspace_size(&in, 1);
+    if ((st = check_ws(ws, ws_bytes, core + gva_bytes(p, d, true))) != KDA_OK) return st;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    char* w = static_cast<char*>(ws) + core;
+    if ((st = gva_expand(p, d, w, in, cs)) != KDA_OK) return st;
+    const size_t one = up((size_t)(p->io == KDA_BF16 ? 2 : 4) * d.Ttot * p->HV * d.D);
+    void* dqx = w + 2 * one;
+    void* dkx = w + 3 * one;
+    st = chunk_bwd_pro(&in, dout, dht, saved, dqx, dkx, dv, dg, dbeta, derase, dwrite, dh0, dA_log, ddt_bias, ws, core,
+                       stream);
+    if (st != KDA_OK) return st;
+    cudaError_t e = traced("k_gva_reduce", cs, [&] {
+        return kda::launch_gva_reduce(d.Ttot, p->H, p->HV / p->H, d.D, p->io == KDA_BF16, dqx, dkx, dq, dk, cs);
+    });
+    return e == cudaSuccess ? KDA_OK : cuda_fail(e, "grouped heads: reduce dq, dk");
+}
+
 kda_status kda_recurrent_fwd(const kda_problem* p, void* o, float* ht, int32_t* err, kda_stream_t stream) {
     Dims d;
     kda_status st = check_dims(p, d);
@@ -640,11 +726,13 @@ kda_status kda_recurrent_fwd(const kda_problem* p, void* o, float* ht, int32_t* 
     if (p->save_policy != 0) return fail(KDA_ERR_INVALID_ARG, "the recurrent forward has no saved buffer: use save_policy 0");
     if (d.Ttot > 0 && !o) return fail(KDA_ERR_INVALID_ARG, "o must be non-NULL");
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-    const kda::Shape s = shape_of(p, d);
+    const kda_problem in = gva(p) ? gva_inner(p, p->q, p->k) : *p;   // value heads; q, k read per group
+    const kda::Shape s = shape_of(&in, d);
+    const int group = gva(p) ? p->HV / p->H : 1;
     cudaError_t e = traced("k_recurrent", cs, [&] {
         return kda::launch_recurrent(s, p->io == KDA_BF16, (int)p->gate, p->T, p->cu_seqlens, p->q, p->k, p->v, p->beta,
                                      p->g, p->h0, o, ht, err, p->A_log, p->dt_bias, p->lower_bound, p->qk_l2norm,
-                                     l2eps(p), cs, kda::Gdn2{p->erase, p->write});
+                                     l2eps(p), cs, kda::Gdn2{p->erase, p->write}, group);
     });
     if (e != cudaSuccess) return cuda_fail(e, "recurrent forward");
     return KDA_OK;

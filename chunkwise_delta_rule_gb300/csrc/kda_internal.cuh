@@ -221,11 +221,17 @@ struct EpilogueArgs {
 int prologue_blocks(int Ttot);
 cudaError_t launch_prologue(const Shape& s, int bf16, int gate, const PrologueArgs& a, cudaStream_t st);
 cudaError_t launch_epilogue(const Shape& s, int bf16, int gate, const EpilogueArgs& a, cudaStream_t st);
+// grouped value heads (kda_gva.cu): q, k copied per value head; dq, dk summed per group
+cudaError_t launch_gva_expand(int Ttot, int HV, int G, int K, int bf16, const void* q, const void* k, void* qx, void* kx,
+                              cudaStream_t st);
+cudaError_t launch_gva_reduce(int Ttot, int H, int G, int K, int bf16, const void* dqx, const void* dkx, void* dq, void* dk,
+                              cudaStream_t st);
 // token-by-token forward (kda_recurrent.cu); T = tokens per sequence when cu is NULL
 cudaError_t launch_recurrent(const Shape& s, int bf16, int gate, int T, const int32_t* cu, const void* q,
                              const void* k, const void* v, const void* beta, const float* g, const float* h0,
                              void* o, float* ht, int32_t* err, const float* A_log, const float* dt_bias,
-                             float lower_bound, int qk_norm, float eps, cudaStream_t st, const Gdn2& gd = Gdn2{});
+                             float lower_bound, int qk_norm, float eps, cudaStream_t st, const Gdn2& gd = Gdn2{},
+                             int group = 1);
 
 cudaError_t launch_prep(const Shape& s, int io_bf16, int gate, const void* q, const void* k,
                         const void* v, const void* beta, const float* g, Table t, Fwd f,

@@ -35,6 +35,7 @@ struct RecIO {
     float lower_bound, eps;
     int qk_norm;
     const void *erase, *write;      // GatedDeltaNet-2 vectors, or NULL (beta rule)
+    int G;                          // value heads per key head (q, k of key head h / G)
 };
 
 __device__ __forceinline__ float rwsum(float x) {
@@ -82,9 +83,9 @@ __device__ __forceinline__ float reduce8(const float (&x)[8], int lane) {
 template <typename TI, int KJ, int GATE>
 struct Tok {
     float k[KJ], q[KJ], a[KJ], eb[KJ], v, b;
-    __device__ __forceinline__ void load(const RecIO& io, size_t row, int K, int V, int col, int lane) {
-        const TI* kp = static_cast<const TI*>(io.k) + row * K + lane;
-        const TI* qp = static_cast<const TI*>(io.q) + row * K + lane;
+    __device__ __forceinline__ void load(const RecIO& io, size_t row, size_t krow, int K, int V, int col, int lane) {
+        const TI* kp = static_cast<const TI*>(io.k) + krow * K + lane;
+        const TI* qp = static_cast<const TI*>(io.q) + krow * K + lane;
 #pragma unroll
         for (int j = 0; j < KJ; ++j) {
             k[j] = ld(kp + 32 * j);
@@ -184,9 +185,10 @@ __global__ void __launch_bounds__(RT) k_recurrent(Shape s, RecIO io) {
         }
     }
     Tok<TI, KJ, GATE> cur, nxt;
-    if (t0 < t1) cur.load(io, (size_t)t0 * H + h, K, V, cme, lane);
+    const int Hk = H / io.G, hk = h / io.G;   // key heads; this value head's key head
+    if (t0 < t1) cur.load(io, (size_t)t0 * H + h, (size_t)t0 * Hk + hk, K, V, cme, lane);
     for (int t = t0; t < t1; ++t) {
-        if (t + 1 < t1) nxt.load(io, (size_t)(t + 1) * H + h, K, V, cme, lane);
+        if (t + 1 < t1) nxt.load(io, (size_t)(t + 1) * H + h, (size_t)(t + 1) * Hk + hk, K, V, cme, lane);
         cur.finish(io, h, K, lane, s.scale);
         // S~ = diag(alpha) S and p = S~^T k (this lane's keys)
         const float (&al)[KJ] = cur.a;
@@ -249,9 +251,10 @@ cudaError_t run_recurrent_k(const Shape& s, int gate, const RecIO& io, cudaStrea
 cudaError_t launch_recurrent(const Shape& s, int bf16, int gate, int T, const int32_t* cu, const void* q,
                              const void* k, const void* v, const void* beta, const float* g, const float* h0,
                              void* o, float* ht, int32_t* err, const float* A_log, const float* dt_bias,
-                             float lower_bound, int qk_norm, float eps, cudaStream_t st, const Gdn2& gd) {
+                             float lower_bound, int qk_norm, float eps, cudaStream_t st, const Gdn2& gd, int group) {
     if (s.V % RV != 0 || (s.K != 64 && s.K != 128)) return cudaErrorInvalidValue;
-    RecIO io{q, k, v, beta, g, h0, cu, o, ht, err, T, A_log, dt_bias, lower_bound, eps, qk_norm, gd.erase, gd.write};
+    RecIO io{q, k, v, beta, g, h0, cu, o, ht, err, T, A_log, dt_bias, lower_bound, eps, qk_norm, gd.erase, gd.write,
+             group};
     if (bf16) return s.K == 128 ? run_recurrent_k<__nv_bfloat16, 128>(s, gate, io, st)
                                 : run_recurrent_k<__nv_bfloat16, 64>(s, gate, io, st);
     return s.K == 128 ? run_recurrent_k<float, 128>(s, gate, io, st) : run_recurrent_k<float, 64>(s, gate, io, st);

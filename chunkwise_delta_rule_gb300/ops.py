@@ -48,7 +48,7 @@ class Problem:
 
     @property
     def state_shape(self):
-        return (self.N, self.c.H, self.c.K, self.c.V)
+        return (self.N, self.c.HV or self.c.H, self.c.K, self.c.V)
 
 
 def _need(cond: bool, msg: str):
@@ -67,10 +67,14 @@ def make_problem(q, k, v, g, beta, *, gate: str, scale: Optional[float] = None,
     form when ``lower_bound`` < 0), with the optional ``dt_bias`` (fp32, [H, K]
     for a per-channel gate, [H] for a scalar one); ``qk_l2norm`` normalises q
     and k per (token, head) first. GatedDeltaNet-2: ``erase`` [B, T, H, K] and
-    ``write`` [B, T, H, V] (the I/O dtype) replace ``beta``, which may be None."""
+    ``write`` [B, T, H, V] (the I/O dtype) replace ``beta``, which may be None.
+    Grouped value heads: v may carry HV = G * H heads (q, k keep H); then every
+    per-head tensor but q and k has HV heads (read H as HV above)."""
     _need(q.dim() == 4 and k.shape == q.shape, "q and k must be [B, T, H, K]")
-    B, T, H, K = q.shape
-    _need(v.dim() == 4 and v.shape[:3] == q.shape[:3], "v must be [B, T, H, V]")
+    B, T, Hk, K = q.shape
+    _need(v.dim() == 4 and v.shape[:2] == q.shape[:2], "v must be [B, T, HV, V]")
+    H = v.shape[2]   # value heads: the head count of every other tensor
+    _need(H % Hk == 0, "the value heads must be a multiple of the key heads")
     V = v.shape[3]
     _need((erase is None) == (write is None), "erase and write come together")
     if erase is not None:
@@ -101,7 +105,8 @@ def make_problem(q, k, v, g, beta, *, gate: str, scale: Optional[float] = None,
         _need(initial_state.dtype == torch.float32 and initial_state.is_contiguous()
               and tuple(initial_state.shape) == (N, H, K, V), "initial_state must be fp32 [N, H, K, V]")
     c = _lib.KdaProblem()
-    c.B, c.T, c.H, c.K, c.V = B, T, H, K, V
+    c.B, c.T, c.H, c.K, c.V = B, T, Hk, K, V
+    c.HV = H if H != Hk else 0
     c.N = N if cu_seqlens is not None else 0
     c.cu_seqlens = None if cu_seqlens is None else cu_seqlens.data_ptr()
     c.io = _lib.DTYPES[_IO[q.dtype]]

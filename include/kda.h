@@ -100,6 +100,11 @@ typedef struct {
      * them (tensor-core, CUDA-core, token-by-token). */
     const void *erase;          /* [B*T, H, K] io dtype */
     const void *write;          /* [B*T, H, V] io dtype */
+    /* Grouped value heads: 0 (or H) for one value head per key head. HV = G * H (G > 1): q and
+     * k keep H key heads; v, beta, g, erase, write, A_log, dt_bias, h0 and the outputs and
+     * gradients of those have HV value heads (read "H" as HV in their shapes above); value
+     * head j reads key head j / G, and dq, dk sum over each group. */
+    int HV;
 } kda_problem;
 
 /* Bytes of device workspace kda_chunk_fwd (for_backward = 0) or kda_chunk_bwd

@@ -24,7 +24,7 @@ def test_library_exports_every_declared_symbol():
     assert "kda_chunk_fwd" in names and "kda_chunk_bwd" in names
     for n in names:
         assert hasattr(lib, n), n
-    assert lib.kda_abi_version() == 3
+    assert lib.kda_abi_version() == 4
 
 
 def _prob(**kw):
@@ -170,3 +170,21 @@ def test_prologue_fields_are_validated_and_sized():
     extra_f = 2 * up(2 * tok) + up(4 * tok)
     assert _ws(p, 0) == core_f + extra_f
     assert _ws(p, 1) == core_b + extra_f + up(4 * nb * 3 * 128) + up(4 * nb * 3)
+
+
+def test_grouped_value_heads_are_validated_and_sized():
+    lib = _lib.load()
+    p = _prob(H=3)
+    p.HV = 4   # not a multiple of H
+    assert lib.kda_chunk_fwd(ctypes.byref(p), ctypes.c_void_p(0x3000), None, None, None, 0, None) == 1
+    assert _ws(p, 0) == 0
+
+    def up(x):
+        return (x + 255) // 256 * 256
+
+    g = _prob(H=2)
+    g.HV = 6
+    flat = _prob(H=6)   # the same problem with one key head per value head
+    copy = up(2 * 2 * 130 * 6 * 128)   # bf16 q (or k) copied per value head
+    assert _ws(g, 0) == _ws(flat, 0) + 2 * copy
+    assert _ws(g, 1) == _ws(flat, 1) + 4 * copy
