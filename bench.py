@@ -270,6 +270,9 @@ def run_ours(args):
         gen = _t.Generator().manual_seed(4242)
         pro["erase"] = (2.0 * _t.sigmoid(_t.randn(case_cpu.k.shape, generator=gen))).to(case_cpu.q.dtype).to(dev)
         pro["write"] = _t.sigmoid(_t.randn(case_cpu.v.shape, generator=gen)).to(case_cpu.q.dtype).to(dev)
+    if args.gva > 1:   # grouped value heads: one q, k per group of value heads
+        case_cpu.q = case_cpu.q[:, :, ::args.gva].contiguous()
+        case_cpu.k = case_cpu.k[:, :, ::args.gva].contiguous()
     case = case_cpu.to(dev)
     lib = _lib.load()
     save = 1 if args.policy == "save" else 0
@@ -384,10 +387,10 @@ def run_ours(args):
         kernels[k] = rec
 
     e2e = None
-    if not args.no_e2e and not args.prologue and not args.gdn2:   # (the end-to-end and CPU legs time the headline problem)
+    if not args.no_e2e and not args.prologue and not args.gdn2 and args.gva <= 1:   # (the end-to-end and CPU legs time the headline problem)
         e2e = run_e2e(args, case_cpu, dev, kda, K)
     cpu = None
-    if rank == 0 and ws == 1 and not args.no_cpu and not args.prologue and not args.gdn2:
+    if rank == 0 and ws == 1 and not args.no_cpu and not args.prologue and not args.gdn2 and args.gva <= 1:
         cpu = cpu_baseline(case_cpu)
 
     if rank == 0:
@@ -401,6 +404,7 @@ def run_ours(args):
                        "policy": args.policy, "parallelism": f"replicas x{ws}",
                        "prologue": ("raw gate activated in the operator (softplus form, A_log, dt_bias) and "
                                     "q/k L2-normalised in the operator") if args.prologue else "off",
+                       "key_heads": case.q.shape[2],
                        "rule": ("GatedDeltaNet-2: erase b = 2 sigmoid(N(0,1)) per key channel, write w = "
                                 "sigmoid(N(0,1)) per value channel") if args.gdn2
                        else "delta rule with beta",
@@ -626,6 +630,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--heads", type=int, default=0, help="restrict the workload to its first H heads (profiling)")
+    ap.add_argument("--gva", type=int, default=1,
+                    help="grouped value heads: this many value heads per key head")
     ap.add_argument("--gdn2", action="store_true",
                     help="the GatedDeltaNet-2 rule (erase/write vectors in place of beta)")
     ap.add_argument("--prologue", action="store_true",
