@@ -259,6 +259,12 @@ def run_ours(args):
     torch.cuda.set_device(dev)
     cfg = CONFIGS[args.config]
     case_cpu = make_config_case(args.config)
+    if args.kv:   # the same workload recipe at other key / value widths
+        from workloads import make_case
+        kk, vv = (int(x) for x in args.kv.split(","))
+        c0 = case_cpu
+        case_cpu = make_case(io=cfg["io"], gate=c0.gate, B=c0.B, T=c0.T, H=c0.H, K=kk, V=vv,
+                             seed=cfg.get("seed", 3), h0=c0.h0 is not None, dht=c0.dht is not None)
     if args.heads:
         case_cpu = heads_subset(case_cpu, args.heads)
     pro = {}
@@ -387,10 +393,11 @@ def run_ours(args):
         kernels[k] = rec
 
     e2e = None
-    if not args.no_e2e and not args.prologue and not args.gdn2 and args.gva <= 1:   # (the end-to-end and CPU legs time the headline problem)
+    if not args.no_e2e and not args.prologue and not args.gdn2 and args.gva <= 1 and not args.kv:   # (the end-to-end and CPU legs time the headline problem)
         e2e = run_e2e(args, case_cpu, dev, kda, K)
     cpu = None
-    if rank == 0 and ws == 1 and not args.no_cpu and not args.prologue and not args.gdn2 and args.gva <= 1:
+    if rank == 0 and ws == 1 and not args.no_cpu and not args.prologue and not args.gdn2 and args.gva <= 1 \
+            and not args.kv:
         cpu = cpu_baseline(case_cpu)
 
     if rank == 0:
@@ -630,6 +637,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--heads", type=int, default=0, help="restrict the workload to its first H heads (profiling)")
+    ap.add_argument("--kv", default="", help="key,value widths (e.g. 80,112) for the same workload recipe")
     ap.add_argument("--gva", type=int, default=1,
                     help="grouped value heads: this many value heads per key head")
     ap.add_argument("--gdn2", action="store_true",

@@ -28,8 +28,7 @@ kda_status check_dims(const kda_problem* p, Dims& d) {
     if (!p) return fail(KDA_ERR_INVALID_ARG, "problem is NULL");
     if (p->B < 1 || p->T < 0 || p->H < 1 || p->K < 1 || p->V < 1)
         return fail(KDA_ERR_INVALID_ARG, "B, H, K, V must be >= 1 and T >= 0");
-    if (p->K != p->V) return fail(KDA_ERR_UNSUPPORTED, "K != V is not built");
-    if (p->K != 64 && p->K != 128) return fail(KDA_ERR_UNSUPPORTED, "K must be 64 or 128");
+    if (p->K > 128 || p->V > 128) return fail(KDA_ERR_UNSUPPORTED, "key or value width above 128 is not built");
     if (p->H > 65535) return fail(KDA_ERR_UNSUPPORTED, "H > 65535");
     if (p->io != KDA_BF16 && p->io != KDA_FP32) return fail(KDA_ERR_INVALID_ARG, "unknown io dtype");
     if (p->gate != KDA_GATE_NONE && p->gate != KDA_GATE_SCALAR && p->gate != KDA_GATE_CHANNEL)
@@ -187,6 +186,75 @@ kda::Shape shape_of(const kda_problem* p, const Dims& d) {
     s.Ttot = d.Ttot;
     s.scale = p->scale > 0.f ? p->scale : 1.0f / sqrtf((float)p->K);
     return s;
+}
+
+// Widths other than K = V = 64 or 128 run zero-padded to D (0: no padding).
+int pad_width(const kda_problem* p) {
+    if (p->K == p->V && (p->K == 64 || p->K == 128)) return 0;
+    return (p->K <= 64 && p->V <= 64) ? 64 : 128;
+}
+// The padded buffers, in a fixed order after the inner problem's workspace (base NULL: size only).
+struct PadBufs {
+    void *q = nullptr, *k = nullptr, *v = nullptr, *erase = nullptr, *write = nullptr, *o = nullptr, *dout = nullptr;
+    void *dq = nullptr, *dk = nullptr, *dv = nullptr, *derase = nullptr, *dwrite = nullptr;
+    float *g = nullptr, *h0 = nullptr, *dtb = nullptr, *ht = nullptr, *dht = nullptr, *dg = nullptr, *dh0 = nullptr,
+          *ddtb = nullptr;
+};
+size_t pad_layout(const kda_problem* p, const Dims& d, bool bwd, char* base, PadBufs& b) {
+    const size_t D = (size_t)pad_width(p), es = p->io == KDA_BF16 ? 2 : 4;
+    const size_t Hv = (size_t)(p->HV ? p->HV : p->H), Hk = (size_t)p->H, T = (size_t)d.Ttot, N = (size_t)d.N;
+    const bool ch = p->gate == KDA_GATE_CHANNEL;
+    size_t n = 0;
+    auto take = [&](size_t bytes) -> char* {
+        char* r = base ? base + n : nullptr;
+        n += up(bytes);
+        return r;
+    };
+    b.q = take(es * T * Hk * D);
+    b.k = take(es * T * Hk * D);
+    b.v = take(es * T * Hv * D);
+    if (ch) b.g = reinterpret_cast<float*>(take(4 * T * Hv * D));
+    if (p->erase) {
+        b.erase = take(es * T * Hv * D);
+        b.write = take(es * T * Hv * D);
+    }
+    if (p->h0) b.h0 = reinterpret_cast<float*>(take(4 * N * Hv * D * D));
+    if (p->dt_bias && ch) b.dtb = reinterpret_cast<float*>(take(4 * Hv * D));
+    b.o = take(es * T * Hv * D);
+    b.ht = reinterpret_cast<float*>(take(4 * N * Hv * D * D));
+    if (bwd) {
+        b.dout = take(es * T * Hv * D);
+        b.dht = reinterpret_cast<float*>(take(4 * N * Hv * D * D));
+        b.dq = take(es * T * Hk * D);
+        b.dk = take(es * T * Hk * D);
+        b.dv = take(es * T * Hv * D);
+        if (ch) b.dg = reinterpret_cast<float*>(take(4 * T * Hv * D));
+        if (p->erase) {
+            b.derase = take(es * T * Hv * D);
+            b.dwrite = take(es * T * Hv * D);
+        }
+        b.dh0 = reinterpret_cast<float*>(take(4 * N * Hv * D * D));
+        if (p->dt_bias && ch) b.ddtb = reinterpret_cast<float*>(take(4 * Hv * D));
+    }
+    return n;
+}
+// The padded problem (sizes only, or pointed at the padded buffers).
+kda_problem pad_inner(const kda_problem* p, const PadBufs* b) {
+    kda_problem c = *p;
+    c.K = c.V = pad_width(p);
+    if (b) {
+        c.q = b->q;
+        c.k = b->k;
+        c.v = b->v;
+        if (b->g) c.g = b->g;
+        if (p->erase) {
+            c.erase = b->erase;
+            c.write = b->write;
+        }
+        c.h0 = b->h0;
+        if (b->dtb) c.dt_bias = b->dtb;
+    }
+    return c;
 }
 
 // Grouped value heads: the problem the rest of the library sees has one key head per value
@@ -364,6 +432,11 @@ size_t kda_workspace_size(const kda_problem* p, int for_backward) {
     Dims d;
     if (check_dims(p, d) != KDA_OK) return 0;
     if (d.Ttot == 0) return 0;
+    if (pad_width(p)) {
+        PadBufs b;
+        const kda_problem in = pad_inner(p, nullptr);
+        return kda_workspace_size(&in, for_backward) + pad_layout(p, d, for_backward != 0, nullptr, b);
+    }
     if (gva(p)) {
         const kda_problem in = gva_inner(p, p->q, p->k);
         return kda_workspace_size(&in, for_backward) + gva_bytes(p, d, for_backward != 0);
@@ -375,6 +448,10 @@ size_t kda_workspace_size(const kda_problem* p, int for_backward) {
 size_t kda_saved_size(const kda_problem* p) {
     Dims d;
     if (check_dims(p, d) != KDA_OK) return 0;
+    if (pad_width(p)) {
+        const kda_problem in = pad_inner(p, nullptr);
+        return kda_saved_size(&in);
+    }
     if (gva(p)) {
         const kda_problem in = gva_inner(p, p->q, p->k);
         return kda_saved_size(&in);
@@ -670,8 +747,8 @@ static kda_status gva_expand(const kda_problem* p, const Dims& d, char* w, kda_p
     return e == cudaSuccess ? KDA_OK : cuda_fail(e, "grouped heads: expand q, k");
 }
 
-kda_status kda_chunk_fwd(const kda_problem* p, void* o, float* ht, void* saved, void* ws, size_t ws_bytes,
-                         kda_stream_t stream) {
+static kda_status chunk_fwd_gva(const kda_problem* p, void* o, float* ht, void* saved, void* ws, size_t ws_bytes,
+                                kda_stream_t stream) {
     if (!p || !gva(p)) return chunk_fwd_pro(p, o, ht, saved, ws, ws_bytes, stream);
     Dims d;
     kda_status st = check_dims(p, d);
@@ -686,9 +763,9 @@ kda_status kda_chunk_fwd(const kda_problem* p, void* o, float* ht, void* saved, 
     return chunk_fwd_pro(&in, o, ht, saved, ws, core, stream);
 }
 
-kda_status kda_chunk_bwd(const kda_problem* p, const void* dout, const float* dht, const void* saved, void* dq,
-                         void* dk, void* dv, float* dg, void* dbeta, void* derase, void* dwrite, float* dh0,
-                         float* dA_log, float* ddt_bias, void* ws, size_t ws_bytes, kda_stream_t stream) {
+static kda_status chunk_bwd_gva(const kda_problem* p, const void* dout, const float* dht, const void* saved, void* dq,
+                                void* dk, void* dv, float* dg, void* dbeta, void* derase, void* dwrite, float* dh0,
+                                float* dA_log, float* ddt_bias, void* ws, size_t ws_bytes, kda_stream_t stream) {
     if (!p || !gva(p))
         return chunk_bwd_pro(p, dout, dht, saved, dq, dk, dv, dg, dbeta, derase, dwrite, dh0, dA_log, ddt_bias, ws,
                              ws_bytes, stream);
@@ -718,12 +795,130 @@ kda_status kda_chunk_bwd(const kda_problem* p, const void* dout, const float* dh
     return e == cudaSuccess ? KDA_OK : cuda_fail(e, "grouped heads: reduce dq, dk");
 }
 
+// Widths other than K = V = 64 or 128: every key- and value-side tensor zero-padded to the
+// working width after the inner problem's workspace, outputs and gradients cropped back.
+struct PadIo {
+    const kda_problem* p;
+    const Dims& d;
+    cudaStream_t cs;
+    cudaError_t e = cudaSuccess;
+    int D() const { return pad_width(p); }
+    long long Hv() const { return p->HV ? p->HV : p->H; }
+    // token rows [rows][w] <-> [rows][D]
+    void rows(bool pad, int es, long long n, int w, const void* src, void* dst) {
+        if (e == cudaSuccess && src && dst)
+            e = traced(pad ? "k_pad" : "k_crop", cs, [&] { return kda::launch_pad(pad, es, n, 1, w, 1, D(), src, dst, cs); });
+    }
+    // states [N * Hv][K][V] <-> [N * Hv][D][D]
+    void states(bool pad, const void* src, void* dst) {
+        if (e == cudaSuccess && src && dst)
+            e = traced(pad ? "k_pad" : "k_crop", cs, [&] {
+                return kda::launch_pad(pad, 4, (long long)d.N * Hv(), p->K, p->V, D(), D(), src, dst, cs);
+            });
+    }
+};
+
+static kda_status pad_inputs(const kda_problem* p, const Dims& d, const PadBufs& b, cudaStream_t cs) {
+    PadIo io{p, d, cs};
+    const int es = p->io == KDA_BF16 ? 2 : 4;
+    const long long T = d.Ttot, Hk = p->H, Hv = io.Hv();
+    io.rows(true, es, T * Hk, p->K, p->q, b.q);
+    io.rows(true, es, T * Hk, p->K, p->k, b.k);
+    io.rows(true, es, T * Hv, p->V, p->v, b.v);
+    io.rows(true, 4, T * Hv, p->K, p->gate == KDA_GATE_CHANNEL ? p->g : nullptr, b.g);
+    io.rows(true, es, T * Hv, p->K, p->erase, b.erase);
+    io.rows(true, es, T * Hv, p->V, p->write, b.write);
+    io.states(true, p->h0, b.h0);
+    io.rows(true, 4, Hv, p->K, b.dtb ? p->dt_bias : nullptr, b.dtb);
+    return io.e == cudaSuccess ? KDA_OK : cuda_fail(io.e, "pad to the working width");
+}
+
+kda_status kda_chunk_fwd(const kda_problem* p, void* o, float* ht, void* saved, void* ws, size_t ws_bytes,
+                         kda_stream_t stream) {
+    if (!p || !pad_width(p)) return chunk_fwd_gva(p, o, ht, saved, ws, ws_bytes, stream);
+    Dims d;
+    kda_status st = check_dims(p, d);
+    if (st != KDA_OK) return st;
+    if ((st = check_inputs(p, d)) != KDA_OK) return st;
+    if (d.Ttot > 0 && !o) return fail(KDA_ERR_INVALID_ARG, "o must be non-NULL");
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    const size_t sb = sizeof(float) * (size_t)d.N * (p->HV ? p->HV : p->H) * p->K * p->V;
+    if (d.Ttot == 0) {   // no tokens: the final state is the initial state
+        if (!ht) return KDA_OK;
+        cudaError_t e = p->h0 ? cudaMemcpyAsync(ht, p->h0, sb, cudaMemcpyDeviceToDevice, cs) : cudaMemsetAsync(ht, 0, sb, cs);
+        return e == cudaSuccess ? KDA_OK : cuda_fail(e, "copy h0");
+    }
+    const kda_problem in0 = pad_inner(p, nullptr);
+    const size_t core = kda_workspace_size(&in0, 0);
+    PadBufs b;
+    if ((st = check_ws(ws, ws_bytes, core + pad_layout(p, d, false, nullptr, b))) != KDA_OK) return st;
+    pad_layout(p, d, false, static_cast<char*>(ws) + core, b);
+    if ((st = pad_inputs(p, d, b, cs)) != KDA_OK) return st;
+    const kda_problem in = pad_inner(p, &b);
+    if ((st = chunk_fwd_gva(&in, b.o, b.ht, saved, ws, core, stream)) != KDA_OK) return st;
+    PadIo io{p, d, cs};
+    io.rows(false, p->io == KDA_BF16 ? 2 : 4, (long long)d.Ttot * io.Hv(), p->V, b.o, o);
+    io.states(false, b.ht, ht);
+    return io.e == cudaSuccess ? KDA_OK : cuda_fail(io.e, "crop from the working width");
+}
+
+kda_status kda_chunk_bwd(const kda_problem* p, const void* dout, const float* dht, const void* saved, void* dq,
+                         void* dk, void* dv, float* dg, void* dbeta, void* derase, void* dwrite, float* dh0,
+                         float* dA_log, float* ddt_bias, void* ws, size_t ws_bytes, kda_stream_t stream) {
+    if (!p || !pad_width(p))
+        return chunk_bwd_gva(p, dout, dht, saved, dq, dk, dv, dg, dbeta, derase, dwrite, dh0, dA_log, ddt_bias, ws,
+                             ws_bytes, stream);
+    Dims d;
+    kda_status st = check_dims(p, d);
+    if (st != KDA_OK) return st;
+    if ((st = check_inputs(p, d)) != KDA_OK) return st;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    const bool ch = p->gate == KDA_GATE_CHANNEL;
+    if (d.Ttot == 0) {   // no tokens: dh0 = dht, parameters get zero gradients
+        const size_t sb = sizeof(float) * (size_t)d.N * (p->HV ? p->HV : p->H) * p->K * p->V;
+        cudaError_t e = cudaSuccess;
+        if (dh0) e = dht ? cudaMemcpyAsync(dh0, dht, sb, cudaMemcpyDeviceToDevice, cs) : cudaMemsetAsync(dh0, 0, sb, cs);
+        const size_t hv = (size_t)(p->HV ? p->HV : p->H);
+        if (e == cudaSuccess && dA_log && p->A_log) e = cudaMemsetAsync(dA_log, 0, 4 * hv, cs);
+        if (e == cudaSuccess && ddt_bias && p->dt_bias) e = cudaMemsetAsync(ddt_bias, 0, 4 * hv * (ch ? p->K : 1), cs);
+        return e == cudaSuccess ? KDA_OK : cuda_fail(e, "empty backward");
+    }
+    if (!dout || !dq || !dk || !dv) return fail(KDA_ERR_INVALID_ARG, "dout, dq, dk and dv must be non-NULL");
+    const kda_problem in0 = pad_inner(p, nullptr);
+    const size_t core = kda_workspace_size(&in0, 1);
+    PadBufs b;
+    if ((st = check_ws(ws, ws_bytes, core + pad_layout(p, d, true, nullptr, b))) != KDA_OK) return st;
+    pad_layout(p, d, true, static_cast<char*>(ws) + core, b);
+    if ((st = pad_inputs(p, d, b, cs)) != KDA_OK) return st;
+    PadIo io{p, d, cs};
+    const int es = p->io == KDA_BF16 ? 2 : 4;
+    const long long T = d.Ttot, Hk = p->H, Hv = io.Hv();
+    io.rows(true, es, T * Hv, p->V, dout, b.dout);
+    io.states(true, dht, b.dht);
+    if (io.e != cudaSuccess) return cuda_fail(io.e, "pad to the working width");
+    const kda_problem in = pad_inner(p, &b);
+    st = chunk_bwd_gva(&in, b.dout, dht ? b.dht : nullptr, saved, b.dq, b.dk, b.dv, ch ? b.dg : dg, dbeta,
+                       p->erase ? b.derase : nullptr, p->erase ? b.dwrite : nullptr, b.dh0, dA_log,
+                       b.ddtb ? b.ddtb : ddt_bias, ws, core, stream);
+    if (st != KDA_OK) return st;
+    io.rows(false, es, T * Hk, p->K, b.dq, dq);
+    io.rows(false, es, T * Hk, p->K, b.dk, dk);
+    io.rows(false, es, T * Hv, p->V, b.dv, dv);
+    if (ch) io.rows(false, 4, T * Hv, p->K, b.dg, dg);
+    io.rows(false, es, T * Hv, p->K, b.derase, derase);
+    io.rows(false, es, T * Hv, p->V, b.dwrite, dwrite);
+    io.states(false, b.dh0, dh0);
+    if (b.ddtb) io.rows(false, 4, Hv, p->K, b.ddtb, ddt_bias);
+    return io.e == cudaSuccess ? KDA_OK : cuda_fail(io.e, "crop from the working width");
+}
+
 kda_status kda_recurrent_fwd(const kda_problem* p, void* o, float* ht, int32_t* err, kda_stream_t stream) {
     Dims d;
     kda_status st = check_dims(p, d);
     if (st != KDA_OK) return st;
     if ((st = check_inputs(p, d)) != KDA_OK) return st;
     if (p->save_policy != 0) return fail(KDA_ERR_INVALID_ARG, "the recurrent forward has no saved buffer: use save_policy 0");
+    if (pad_width(p)) return fail(KDA_ERR_UNSUPPORTED, "the token-by-token forward needs K = V = 64 or 128");
     if (d.Ttot > 0 && !o) return fail(KDA_ERR_INVALID_ARG, "o must be non-NULL");
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     const kda_problem in = gva(p) ? gva_inner(p, p->q, p->k) : *p;   // value heads; q, k read per group

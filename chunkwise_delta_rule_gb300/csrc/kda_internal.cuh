@@ -221,6 +221,9 @@ struct EpilogueArgs {
 int prologue_blocks(int Ttot);
 cudaError_t launch_prologue(const Shape& s, int bf16, int gate, const PrologueArgs& a, cudaStream_t st);
 cudaError_t launch_epilogue(const Shape& s, int bf16, int gate, const EpilogueArgs& a, cudaStream_t st);
+// unequal or narrower widths (kda_pad.cu): [M][R][C] <-> [M][Rd][Cd], zero fill (es = element bytes)
+cudaError_t launch_pad(bool pad, int es, long long M, int R, int C, int Rd, int Cd, const void* src, void* dst,
+                       cudaStream_t st);
 // grouped value heads (kda_gva.cu): q, k copied per value head; dq, dk summed per group
 cudaError_t launch_gva_expand(int Ttot, int HV, int G, int K, int bf16, const void* q, const void* k, void* qx, void* kx,
                               cudaStream_t st);

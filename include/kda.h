@@ -63,7 +63,8 @@ typedef enum { KDA_GATE_NONE = 0, KDA_GATE_SCALAR = 1, KDA_GATE_CHANNEL = 2 } kd
 
 typedef struct {
     int B, T, H, K, V;          /* batch, tokens per sequence (total tokens when packed),
-                                   heads, key width, value width */
+                                   heads, key width, value width (each 1..128; other than
+                                   K = V = 64 or 128 the chunked calls run zero-padded) */
     int N;                      /* packed sequences (used only when cu_seqlens != NULL) */
     const int32_t *cu_seqlens;  /* device, N+1 non-decreasing token offsets, first 0,
                                    last B*T; NULL for equal-length sequences */

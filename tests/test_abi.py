@@ -90,8 +90,8 @@ def test_workspace_size_arithmetic():
 
 
 @pytest.mark.parametrize("kw,status", [
-    (dict(K=96, V=96), 2),
-    (dict(K=128, V=64), 2),
+    (dict(K=192, V=192), 2),
+    (dict(K=128, V=160), 2),
     (dict(B=0), 1),
     (dict(gate=7), 1),
     (dict(io=5), 1),
@@ -188,3 +188,24 @@ def test_grouped_value_heads_are_validated_and_sized():
     copy = up(2 * 2 * 130 * 6 * 128)   # bf16 q (or k) copied per value head
     assert _ws(g, 0) == _ws(flat, 0) + 2 * copy
     assert _ws(g, 1) == _ws(flat, 1) + 4 * copy
+
+
+def test_unequal_widths_pad_to_the_working_width():
+    def up(x):
+        return (x + 255) // 256 * 256
+
+    lib = _lib.load()
+    p = _prob(K=80, V=112)              # bf16, channel gate, B=2, T=130, H=3: runs at 128
+    work = _prob(K=128, V=128)
+    T, H, D = 2 * 130, 3, 128
+    # q, k, v, g (fp32), o, ht (fp32) at the working width
+    pad_f = 3 * up(2 * T * H * D) + up(4 * T * H * D) + up(2 * T * H * D) + up(4 * 2 * H * D * D)
+    assert _ws(p, 0) == _ws(work, 0) + pad_f
+    # backward adds dout, dht, dq, dk, dv, dg, dh0
+    pad_b = pad_f + up(2 * T * H * D) + up(4 * 2 * H * D * D) + 3 * up(2 * T * H * D) + up(4 * T * H * D) \
+        + up(4 * 2 * H * D * D)
+    assert _ws(p, 1) == _ws(work, 1) + pad_b
+    small = _prob(K=32, V=48)           # both within 64: runs at 64
+    assert _ws(small, 0) > 0
+    z = ctypes.c_void_p(0x3000)
+    assert lib.kda_recurrent_fwd(ctypes.byref(p), z, None, None, None) == 2

@@ -1,0 +1,93 @@
+"""GPU parity at key and value widths other than K = V = 64 or 128 (served
+zero-padded to the working width and cropped back), alone and together with
+grouped value heads, the GatedDeltaNet-2 vectors and the prologue, against
+the FP64 oracle at the true widths."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle.cases import packed, run_oracle_prologue_arrays
+from tests.helpers import check_close, np64
+from workloads import make_case
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"fp32": 1e-4, "bf16": 2e-2}
+
+
+def width_case(io, gate, B, T, H, K, V, seed):
+    return make_case(io=io, gate=gate, B=B, T=T, H=H, K=K, V=V, seed=seed)
+
+
+def run_both(case, G=1, gdn2=False, prologue=False):
+    import chunkwise_delta_rule_gb300 as kda
+    gen = torch.Generator().manual_seed(777)
+    BT, HV = case.B * case.T, case.H
+    qk = (case.q[:, :, ::G].contiguous(), case.k[:, :, ::G].contiguous())
+    if prologue:   # raw q, k and gate
+        qk = tuple((x.float() * (torch.rand(x.shape[:3] + (1,), generator=gen) * 2 + 0.5)).to(x.dtype) for x in qk)
+        case.g = torch.randn(case.g.shape, generator=gen) * 0.5
+        A = torch.log(torch.rand(HV, generator=gen) * 3 + 1)
+        dtb = torch.randn((HV, case.K), generator=gen) * 0.3 - 4.0
+    b = w = None
+    if gdn2:
+        b = (2 * torch.sigmoid(torch.randn(case.k.shape, generator=gen))).to(case.q.dtype)
+        w = torch.sigmoid(torch.randn(case.v.shape, generator=gen)).to(case.q.dtype)
+    # oracle at the true widths, q and k repeated per value head
+    case.q, case.k = qk[0].repeat_interleave(G, 2), qk[1].repeat_interleave(G, 2)
+    p = packed(case)
+    ref = run_oracle_prologue_arrays(p["q"], p["k"], p["v"], None if gdn2 else p["beta"], p["g"],
+                                     A_log=np64(A) if prologue else None, dt_bias=np64(dtb) if prologue else None,
+                                     lower_bound=0.0, eps=1e-6, scale=case.scale, gate=case.gate,
+                                     seq_starts=case.seq_starts, h0=p["h0"], do=p["do"], dht=p["dht"],
+                                     qk_norm=prologue, erase=None if b is None else np64(b).reshape(BT, HV, -1),
+                                     write=None if w is None else np64(w).reshape(BT, HV, -1))
+    for name in ("dq", "dk"):
+        ref[name] = ref[name].reshape(BT, HV // G, G, -1).sum(axis=2)
+    c = case.to("cuda")
+    extra = dict(A_log=A.cuda(), dt_bias=dtb.cuda(), qk_l2norm=True) if prologue else {}
+    if gdn2:
+        extra.update(erase=b.cuda(), write=w.cuda())
+    prob = kda.make_problem(qk[0].cuda(), qk[1].cuda(), c.v, c.g, None if gdn2 else c.beta, gate=case.gate,
+                            scale=case.scale, initial_state=c.h0, **extra)
+    o, ht, sv = kda.kda_chunk_fwd(prob)
+    r = kda.kda_chunk_bwd(prob, c.do, c.dht, saved=sv)
+    torch.cuda.synchronize()
+    got = dict(o=o, ht=ht, dq=r[0], dk=r[1], dv=r[2], dg=r[3], dbeta=r[4], dh0=r[5])
+    if prologue:
+        got.update(dA_log=r[6], ddt_bias=r[7])
+    if gdn2:
+        got.update(derase=r[-2], dwrite=r[-1])
+    return got, ref
+
+
+def compare(case, got, ref, G, tol):
+    BT, HV = case.B * case.T, case.H
+    for name, x in got.items():
+        if x is None:
+            continue
+        a = np64(x)
+        if name in ("o", "dv", "derase", "dwrite"):
+            a = a.reshape(BT, HV, -1)
+        elif name in ("dq", "dk"):
+            a = a.reshape(BT, HV // G, -1)
+        elif name == "dbeta":
+            a = a.reshape(BT, HV)
+        elif name == "dg":
+            a = a.reshape(ref["dg"].shape)
+        check_close(name, a, ref[name], tol)
+
+
+@pytest.mark.parametrize("io,gate,K,V", [("bf16", "channel", 80, 112), ("fp32", "channel", 32, 48),
+                                         ("bf16", "scalar", 128, 64), ("fp32", "none", 96, 128)])
+def test_unequal_widths_match_oracle(io, gate, K, V):
+    case = width_case(io, gate, 2, 100, 2, K, V, 101)
+    got, ref = run_both(case)
+    compare(case, got, ref, 1, TOL[io])
+
+
+def test_widths_with_grouped_heads_gdn2_and_prologue():
+    case = width_case("bf16", "channel", 1, 90, 4, 96, 80, 102)
+    got, ref = run_both(case, G=2, gdn2=True, prologue=True)
+    compare(case, got, ref, 2, TOL["bf16"])
