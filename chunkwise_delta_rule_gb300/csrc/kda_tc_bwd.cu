@@ -62,7 +62,11 @@ constexpr int S_QG = 32768;     // Q_g [64][128] 16 KB
 constexpr int S_W = 49152;      // W   [64][128] 16 KB
 constexpr int S_DO = 65536;     // dO  [64][128] 16 KB, TMA (read MN-major as the A operand dO^T)
 constexpr int B_STG = 81920;
-constexpr int B_LAM = B_STAGE + 2 * B_STG;     // lambda [128] fp32
+// S+bar of one chunk and P of the chunk after it as tile images, written to HBM by the issuer
+// (one bulk copy each) after the next hand-over
+constexpr int B_SST = B_STAGE + 2 * B_STG;     // S+bar [128][128] bf16 32 KB
+constexpr int B_PST = B_SST + D * D * 2;       // P     [64][128]  bf16 16 KB
+constexpr int B_LAM = B_PST + BT * D * 2;      // lambda [128] fp32
 constexpr int B_TST = B_LAM + 512;             // per-warp transpose staging, 8 x 1280 B
 constexpr int B_BAR = B_TST + 8 * 1280;
 constexpr int BSCAN_SMEM = B_BAR + 64 + 1024;
@@ -190,17 +194,42 @@ __device__ __forceinline__ void bscan_compute(const Shape& s, const float* __res
         tc::tmem_wait_st();
         tc::fence_before_sync();
         tc::named_sync(NB_AR, ST_ALL);
-        // 4. while the update runs: S+bar of this chunk and P of the later one to HBM
-        bf16* SBP = b.SBP + ch * D * D;
+        // 4. while the update runs: S+bar of this chunk and P of the later one as tile images into
+        //    the staging area (the issuer copies them to HBM after the next hand-over)
+        // A lane holds bf16 pairs along keys for its value column; neighbouring lanes swap halves
+        // so that each writes pairs along values (one 32-bit store per pair of rows)
+        const bool odd = lane & 1;
+        // the staging addresses are loop-invariant; an opaque zero keeps the compiler from holding
+        // all of them in registers across the chunk loop
+        int col2;
+        asm volatile("mov.b32 %0, %1;" : "=r"(col2) : "r"(vcol & ~1));
+        auto put2 = [&](uint16_t* img, int R, int row0, uint32_t mine) {
+            const uint32_t other = __shfl_xor_sync(0xffffffffu, mine, 1);
+            const uint32_t w = odd ? __byte_perm(other, mine, 0x7632) : __byte_perm(mine, other, 0x5410);
+            *reinterpret_cast<uint32_t*>(img + tile_el(R, row0 + (odd ? 1 : 0), col2)) = w;
+        };
+        {
+            uint16_t* hs = reinterpret_cast<uint16_t*>(base + B_SST);
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
-            tc::warp_store_t16_img_packed(tst, &sp[q4 >> 1][8 * (q4 & 1)], SBP, D, kb + 16 * q4, 32 * quad, lane);
+            for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+                for (int m = 0; m < 8; ++m) put2(hs, D, kb + 16 * q4 + 2 * m, sp[q4 >> 1][8 * (q4 & 1) + m]);
+        }
         if (it > 0) {
             // P of the later chunk: one barrier per TMEM buffer, so the commit of this chunk's P
             // (already possible here) cannot be mistaken for it
             wait_one(&bar[2 + ((it - 1) & 1)], ((it - 1) >> 1) & 1);
-            store_p(c + 1, (it - 1) & 1);
+            float pv[2][16];
+            const uint32_t tp = tl + T_P + 64 * ((it - 1) & 1);
+            tc::tmem_ld16(tp + ib, pv[0]);
+            tc::tmem_ld16(tp + ib + 16, pv[1]);
+            tc::tmem_wait_ld();
+            uint16_t* ps = reinterpret_cast<uint16_t*>(base + B_PST);
+#pragma unroll
+            for (int m = 0; m < 16; ++m)
+                put2(ps, BT, ib + 2 * m, tc::pack_bf16(pv[m >> 3][(2 * m) & 15], pv[m >> 3][(2 * m + 1) & 15]));
         }
+        tc::fence_async_smem();
     }
     if (c1 > c0) {
         const int last = c1 - 1 - c0;
@@ -222,7 +251,7 @@ __device__ __forceinline__ void bscan_compute(const Shape& s, const float* __res
 
 // Issuer warp: bulk / TMA fills (lane 0) and the three MMA groups of every
 // chunk (warp-uniform descriptors, one elected lane issuing).
-__device__ __forceinline__ void bscan_issue(const Shape& s, const Table& t, const FwdTC& f,
+__device__ __forceinline__ void bscan_issue(const Shape& s, const Table& t, const FwdTC& f, const BwdTC& b,
                                             const CUtensorMap* tmo, uint32_t sb, uint64_t* bar, uint64_t* full,
                                             uint32_t tb, int h, int c0, int c1, int& filled, int& waited) {
     const int lane = threadIdx.x & 31;
@@ -258,6 +287,14 @@ __device__ __forceinline__ void bscan_issue(const Shape& s, const Table& t, cons
                            &full[stage ^ 1]);
                 ++filled;
                 tok_next = (c - 2 >= c0) ? t.chunk_tok0[c - 2] : 0;
+            }
+            // S+bar of the later chunk c+1 and P of chunk c+2, staged during the last iteration;
+            // the staging area is rewritten after the next hand-over, so their reads must be done
+            if (it >= 1) {
+                tc::bulk_s2g(b.SBP + ((size_t)(c + 1) * H + h) * D * D, sb + B_SST, D * D * 2);
+                if (it >= 2) tc::bulk_s2g(b.P + ((size_t)(c + 2) * H + h) * BT * D, sb + B_PST, BT * D * 2);
+                tc::bulk_commit();
+                tc::bulk_wait_read();
             }
         }
         __syncwarp();
@@ -312,7 +349,7 @@ __global__ void __launch_bounds__(ST_ALL, 1)
     tc::fence_after_sync();
     const uint32_t tb = *tslot;
     if (issuer)
-        bscan_issue(s, t, f, &tmo, sb, bar, full, tb, h, c0, c1, filled, waited);
+        bscan_issue(s, t, f, b, &tmo, sb, bar, full, tb, h, c0, c1, filled, waited);
     else
         bscan_compute(s, dht, t, f, b, dh0, base, bar, tb, nseq, h, c0, c1);
     // a bulk fill still in flight (only after a timeout) lands before the CTA leaves
@@ -320,6 +357,13 @@ __global__ void __launch_bounds__(ST_ALL, 1)
         for (; waited < filled; ++waited) tc::mbar_wait(&full[waited & 1], (waited >> 1) & 1);
     tc::fence_before_sync();
     __syncthreads();
+    // S+bar of the first chunk and P of the one after it, staged in the last iteration
+    if (issuer && (tid & 31) == 0 && c1 > c0) {
+        tc::bulk_s2g(b.SBP + ((size_t)c0 * s.H + h) * D * D, sb + B_SST, D * D * 2);
+        if (c1 - c0 >= 2) tc::bulk_s2g(b.P + ((size_t)(c0 + 1) * s.H + h) * BT * D, sb + B_PST, BT * D * 2);
+        tc::bulk_commit();
+        tc::bulk_wait_all();
+    }
     if (warp == 0) tc::tmem_dealloc(tb, 512);
 }
 
@@ -439,7 +483,7 @@ __device__ __forceinline__ bool cons_wait(uint64_t* b, int& w, int32_t* err) {
     return ok;
 }
 
-template <int GATE>
+template <int GATE, bool GD2>
 __global__ void __launch_bounds__(CT, 1)
     k_bwd_consumer_tc(Shape s, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmo, const __grid_constant__ CUtensorMap tmg,
@@ -523,7 +567,7 @@ __global__ void __launch_bounds__(CT, 1)
             }
         }
         const float beta_r =
-            (k == 0) ? ((tid < BT && tid < n && !gd.erase) ? bfx(beta + (size_t)(tok0 + tid) * H + h) : 0.f)
+            (k == 0) ? ((tid < BT && tid < n && !GD2) ? bfx(beta + (size_t)(tok0 + tid) * H + h) : 0.f)
                      : __bfloat162float(beta_nx);
         // the G tile for a scalar gate (or zeros): tile C_A is free since the previous unit's F2
         if (GATE != 2) {
@@ -632,7 +676,7 @@ __global__ void __launch_bounds__(CT, 1)
                 const bf16* pp2 = reinterpret_cast<const bf16*>(&pp);
                 const bf16* vv2 = reinterpret_cast<const bf16*>(&vv);
                 uint32_t out[4], wout[4];
-                if (gd.write) {   // GatedDeltaNet-2: dv = w .* P, dw = v .* P
+                if (GD2) {   // GatedDeltaNet-2: dv = w .* P, dw = v .* P
                     const uint4 ww = *reinterpret_cast<const uint4*>(static_cast<const bf16*>(gd.write) + tok * D + cc * 8);
                     const bf16* ww2 = reinterpret_cast<const bf16*>(&ww);
 #pragma unroll
@@ -703,7 +747,7 @@ __global__ void __launch_bounds__(CT, 1)
                     const float al = (GATE == 2) ? sA[aidx(j, kr)] : 1.f;
                     const bool in = j < n;
                     kz[e] = in ? ((GATE == 2) ? kv * tc::rcp_approx(al) : kv) : 0.f;
-                    const float eb = gd.erase ? (in ? bfx(static_cast<const bf16*>(gd.erase) +
+                    const float eb = GD2 ? (in ? bfx(static_cast<const bf16*>(gd.erase) +
                                                           ((size_t)(tok0 + j) * H + h) * D + kr) : 0.f)
                                               : sBeta[j];
                     ea[e] = in ? eb * kv * al : 0.f;
@@ -777,7 +821,7 @@ __global__ void __launch_bounds__(CT, 1)
                 float tq[16], tp[16];
                 // GatedDeltaNet-2 key rows: the erase vector on columns cb0+cb.. of token i
                 uint4 eb4[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
-                if (gd.erase && !isQ && i < n) {
+                if (GD2 && !isQ && i < n) {
                     const uint4* ep = reinterpret_cast<const uint4*>(static_cast<const bf16*>(gd.erase) +
                                                                      ((size_t)(tok0 + i) * H + h) * D + cb0 + cb);
                     eb4[0] = ep[0];
@@ -803,17 +847,17 @@ __global__ void __launch_bounds__(CT, 1)
                     } else {
                         const float Et = fac * tq[jj] - gam * tp[jj];               // gamma * E_bar
                         const float kv = xq;
-                        const float be = gd.erase ? __bfloat162float(ebv[jj]) : bt;
+                        const float be = GD2 ? __bfloat162float(ebv[jj]) : bt;
                         sDK[i * LG + kr] = be * Et;
                         tq[jj] = be * kv * Et;                                      // erase part of G_bar
                         part = fmaf(kv, Et, part);
-                        if (gd.erase) {   // db = K gamma .* E_bar, packed in pairs (tp[jj] is spent)
+                        if (GD2) {   // db = K gamma .* E_bar, packed in pairs (tp[jj] is spent)
                             if (jj & 1) dbw[jj / 2] = tc::pack_bf16(tp[jj - 1], kv * Et);
                             else tp[jj] = kv * Et;
                         }
                     }
                 }
-                if (gd.erase && !isQ && i < n) {
+                if (GD2 && !isQ && i < n) {
                     uint4* dst = reinterpret_cast<uint4*>(static_cast<bf16*>(gd.derase) +
                                                           ((size_t)(tok0 + i) * H + h) * D + cb0 + cb);
                     dst[0] = make_uint4(dbw[0], dbw[1], dbw[2], dbw[3]);
@@ -876,7 +920,7 @@ __global__ void __launch_bounds__(CT, 1)
                 }
                 // kept as bf16 so the load stays in flight until the next unit starts
                 if (tid < BT)
-                    beta_nx = (tid < nm[1] && !gd.erase) ? beta[(size_t)(nm[2] + tid) * H + nh] : __float2bfloat16_rn(0.f);
+                    beta_nx = (tid < nm[1] && !GD2) ? beta[(size_t)(nm[2] + tid) * H + nh] : __float2bfloat16_rn(0.f);
             }
         }
         // ---- F3: dk, dbeta; key rows add the erase part of G_bar; the endpoint terms of the last
@@ -891,7 +935,7 @@ __global__ void __launch_bounds__(CT, 1)
                 *reinterpret_cast<uint4*>(dk + ((size_t)(tok0 + r) * H + h) * D + cc * 8) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
             }
         }
-        if (tid < BT && tid < n && !gd.erase)
+        if (tid < BT && tid < n && !GD2)
             dbeta[(size_t)(tok0 + tid) * H + h] = __float2bfloat16_rn(sRowP[tid] + sRowP[BT + tid] + sRowP[2 * BT + tid] +
                                                                       sRowP[3 * BT + tid] + sDbw[tid]);
         if (GATE != 0) {
@@ -974,11 +1018,11 @@ __global__ void __launch_bounds__(CT, 1)
     if (warp == 0) tc::tmem_dealloc(tb, 512);
 }
 
-template <int GATE>
+template <int GATE, bool GD2>
 cudaError_t run_consumer(const Shape& s, const void* q, const void* k, const void* v, const void* beta,
                          const float* g, const void* dout, Table t, FwdTC f, BwdTC b, void* dq, void* dk,
                          void* dv, void* dbeta, float* dg, cudaStream_t st, const Gdn2& gd) {
-    cudaError_t e = set_smem_once<k_bwd_consumer_tc<GATE>>(CONS_SMEM);
+    cudaError_t e = set_smem_once<k_bwd_consumer_tc<GATE, GD2>>(CONS_SMEM);
     if (e != cudaSuccess) return e;
     CUtensorMap mq, mk, mo, mg, mv;
     memset(&mg, 0, sizeof(mg));
@@ -989,7 +1033,7 @@ cudaError_t run_consumer(const Shape& s, const void* q, const void* k, const voi
     const long units = (long)s.NC * s.H;
     if (units <= 0) return cudaSuccess;
     const int grid = (int)(units < sm_count() ? units : sm_count());   // one CTA per SM, persistent
-    k_bwd_consumer_tc<GATE><<<grid, CT, CONS_SMEM, st>>>(s, mq, mk, mo, mg, mv, (const bf16*)beta, g, t, f, b,
+    k_bwd_consumer_tc<GATE, GD2><<<grid, CT, CONS_SMEM, st>>>(s, mq, mk, mo, mg, mv, (const bf16*)beta, g, t, f, b,
                                                          (bf16*)dq, (bf16*)dk, (bf16*)dv, (bf16*)dbeta, dg, gd);
     return cudaGetLastError();
 }
@@ -1012,9 +1056,12 @@ cudaError_t launch_bwd_consumer_tc(const Shape& s, int gate, const void* q, cons
                                    BwdTC b, void* dq, void* dk, void* dv, void* dbeta, float* dg,
                                    cudaStream_t st, const Gdn2& gd) {
     switch (gate) {
-        case 0: return run_consumer<0>(s, q, k, v, beta, g, dout, t, f, b, dq, dk, dv, dbeta, dg, st, gd);
-        case 1: return run_consumer<1>(s, q, k, v, beta, g, dout, t, f, b, dq, dk, dv, dbeta, dg, st, gd);
-        default: return run_consumer<2>(s, q, k, v, beta, g, dout, t, f, b, dq, dk, dv, dbeta, dg, st, gd);
+        case 0: return gd.erase ? run_consumer<0, true>(s, q, k, v, beta, g, dout, t, f, b, dq, dk, dv, dbeta, dg, st, gd)
+                                : run_consumer<0, false>(s, q, k, v, beta, g, dout, t, f, b, dq, dk, dv, dbeta, dg, st, gd);
+        case 1: return gd.erase ? run_consumer<1, true>(s, q, k, v, beta, g, dout, t, f, b, dq, dk, dv, dbeta, dg, st, gd)
+                                : run_consumer<1, false>(s, q, k, v, beta, g, dout, t, f, b, dq, dk, dv, dbeta, dg, st, gd);
+        default: return gd.erase ? run_consumer<2, true>(s, q, k, v, beta, g, dout, t, f, b, dq, dk, dv, dbeta, dg, st, gd)
+                                 : run_consumer<2, false>(s, q, k, v, beta, g, dout, t, f, b, dq, dk, dv, dbeta, dg, st, gd);
     }
 }
 

@@ -170,7 +170,7 @@ static_assert(P_ALPHA + 4 * BT * LG <= P_MISC, "the G tile overlaps the constant
 static_assert(P_TMP + 4 * 32 * LT2 <= 16384, "inverse scratch overlaps E'");
 static_assert(BT * LW * 2 <= P_B1, "W staging overlaps L^T");
 
-template <int GATE, bool BWD>
+template <int GATE, bool BWD, bool GD2>
 __global__ void __launch_bounds__(PT, 2)
     k_prep_tc(Shape s, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
               const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmg,
@@ -213,7 +213,7 @@ __global__ void __launch_bounds__(PT, 2)
         tc::tma_load3(sb + P_V + 8192, &tmv, 64, h, tok0, bld);
         if (GATE == 2) tc::tma_load3(sb + P_ALPHA, &tmg, 0, h, tok0, bld);
     }
-    const float beta_r = (tid < BT && tid < n && !gd.erase) ? bfx(beta + (size_t)(tok0 + tid) * H + h) : 0.f;
+    const float beta_r = (tid < BT && tid < n && !GD2) ? bfx(beta + (size_t)(tok0 + tid) * H + h) : 0.f;
     if (GATE != 2) {
         // scalar gate: the G tile repeats the token's log-decay; no gate: zeros
         for (int idx = tid; idx < BT * D / 4; idx += PT) {
@@ -308,7 +308,7 @@ __global__ void __launch_bounds__(PT, 2)
             // GatedDeltaNet-2: the erase vector on E's key rows in place of beta, and V scaled by
             // the write vector in place (U = A (w .* V)); both read straight from HBM
             uint4 er4 = make_uint4(0, 0, 0, 0);
-            if (gd.erase && i < n) {
+            if (GD2 && i < n) {
                 const size_t o = ((size_t)(tok0 + i) * H + h) * D + c8;
                 er4 = *reinterpret_cast<const uint4*>(static_cast<const bf16*>(gd.erase) + o);
                 const uint4 wr4 = *reinterpret_cast<const uint4*>(static_cast<const bf16*>(gd.write) + o);
@@ -322,7 +322,7 @@ __global__ void __launch_bounds__(PT, 2)
                     pv[e / 2] = tc::pack_bf16(__bfloat162float(wv[e]) * __bfloat162float(vv[e]),
                                               __bfloat162float(wv[e + 1]) * __bfloat162float(vv[e + 1]));
                 *vp = make_uint4(pv[0], pv[1], pv[2], pv[3]);
-            } else if (gd.erase) {
+            } else if (GD2) {
                 *reinterpret_cast<uint4*>(base + P_V + tc::sw128_off(BT, i, c8 * 2)) = make_uint4(0, 0, 0, 0);
             }
             const bf16* ev = reinterpret_cast<const bf16*>(&er4);
@@ -338,7 +338,7 @@ __global__ void __launch_bounds__(PT, 2)
                 const float k0 = __bfloat162float(kv[e]), k1 = __bfloat162float(kv[e + 1]);
                 const float q0 = scale * __bfloat162float(qv[e]) * a0, q1 = scale * __bfloat162float(qv[e + 1]) * a1;
                 const float z0 = k0 * r0, z1 = k1 * r1;
-                const float b0 = gd.erase ? __bfloat162float(ev[e]) : bt, b1 = gd.erase ? __bfloat162float(ev[e + 1]) : bt;
+                const float b0 = GD2 ? __bfloat162float(ev[e]) : bt, b1 = GD2 ? __bfloat162float(ev[e + 1]) : bt;
                 pe[e / 2] = tc::pack_bf16(b0 * k0 * a0, b1 * k1 * a1);
                 pq[e / 2] = tc::pack_bf16(q0, q1);
                 pz[e / 2] = tc::pack_bf16(z0, z1);
@@ -428,7 +428,7 @@ __global__ void __launch_bounds__(PT, 2)
 #pragma unroll 1
             for (int st = 0; st < 4; ++st)
                 tc::mma_bf16(tb + 128, tc::sdesc_mn(sb + P_V, BT * 128, st),
-                             tc::sdesc_k(sb + (gd.erase ? P_BA : P_BB), BT, st), id, st > 0);
+                             tc::sdesc_k(sb + (GD2 ? P_BA : P_BB), BT, st), id, st > 0);
             tc::mma_commit(bar);
         }
         ok = wait_all(bar, 1, t.err);
@@ -891,10 +891,10 @@ __global__ void __launch_bounds__(ST_ALL, 1)
     if (warp == 0) tc::tmem_dealloc(tb, 512);
 }
 
-template <int GATE, bool BWD>
+template <int GATE, bool BWD, bool GD2>
 cudaError_t run_prep(const Shape& s, const void* q, const void* k, const void* v, const void* beta,
                      const float* g, Table t, FwdTC f, cudaStream_t st, const Gdn2& gd) {
-    cudaError_t e = set_smem_once<k_prep_tc<GATE, BWD>>(PREP_SMEM);
+    cudaError_t e = set_smem_once<k_prep_tc<GATE, BWD, GD2>>(PREP_SMEM);
     if (e != cudaSuccess) return e;
     e = cudaMemsetAsync(f.WLIST, 0, sizeof(int32_t), st);   // the list of wide chunks starts empty
     if (e != cudaSuccess) return e;
@@ -904,7 +904,7 @@ cudaError_t run_prep(const Shape& s, const void* q, const void* k, const void* v
         !tmap_rows_bf16(&mv, v, s.Ttot, s.H, D) || (GATE == 2 && !tmap_rows_f32(&mg, g, s.Ttot, s.H, D)))
         return cudaErrorInvalidValue;
     dim3 grid(s.NC, s.H);
-    k_prep_tc<GATE, BWD><<<grid, PT, PREP_SMEM, st>>>(s, mq, mk, mv, mg, (const bf16*)beta, g, t, f, gd);
+    k_prep_tc<GATE, BWD, GD2><<<grid, PT, PREP_SMEM, st>>>(s, mq, mk, mv, mg, (const bf16*)beta, g, t, f, gd);
     return cudaGetLastError();
 }
 
@@ -927,15 +927,15 @@ cudaError_t launch_prep_tc(const Shape& s, int gate, int for_bwd, const void* q,
                            cudaStream_t st, const Gdn2& gd) {
     if (for_bwd) {
         switch (gate) {
-            case 0: return run_prep<0, true>(s, q, k, v, beta, g, t, f, st, gd);
-            case 1: return run_prep<1, true>(s, q, k, v, beta, g, t, f, st, gd);
-            default: return run_prep<2, true>(s, q, k, v, beta, g, t, f, st, gd);
+            case 0: return (gd.erase ? run_prep<0, true, true>(s, q, k, v, beta, g, t, f, st, gd) : run_prep<0, true, false>(s, q, k, v, beta, g, t, f, st, gd));
+            case 1: return (gd.erase ? run_prep<1, true, true>(s, q, k, v, beta, g, t, f, st, gd) : run_prep<1, true, false>(s, q, k, v, beta, g, t, f, st, gd));
+            default: return (gd.erase ? run_prep<2, true, true>(s, q, k, v, beta, g, t, f, st, gd) : run_prep<2, true, false>(s, q, k, v, beta, g, t, f, st, gd));
         }
     }
     switch (gate) {
-        case 0: return run_prep<0, false>(s, q, k, v, beta, g, t, f, st, gd);
-        case 1: return run_prep<1, false>(s, q, k, v, beta, g, t, f, st, gd);
-        default: return run_prep<2, false>(s, q, k, v, beta, g, t, f, st, gd);
+        case 0: return (gd.erase ? run_prep<0, false, true>(s, q, k, v, beta, g, t, f, st, gd) : run_prep<0, false, false>(s, q, k, v, beta, g, t, f, st, gd));
+        case 1: return (gd.erase ? run_prep<1, false, true>(s, q, k, v, beta, g, t, f, st, gd) : run_prep<1, false, false>(s, q, k, v, beta, g, t, f, st, gd));
+        default: return (gd.erase ? run_prep<2, false, true>(s, q, k, v, beta, g, t, f, st, gd) : run_prep<2, false, false>(s, q, k, v, beta, g, t, f, st, gd));
     }
 }
 
