@@ -487,7 +487,8 @@ template <int GATE, bool GD2>
 __global__ void __launch_bounds__(CT, 1)
     k_bwd_consumer_tc(Shape s, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmo, const __grid_constant__ CUtensorMap tmg,
-                      const __grid_constant__ CUtensorMap tmv, const bf16* __restrict__ beta,
+                      const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdg,
+                      const bf16* __restrict__ beta,
                       const float* __restrict__ g, Table t, FwdTC f, BwdTC bw, bf16* __restrict__ dq,
                       bf16* __restrict__ dk, bf16* __restrict__ dv, bf16* __restrict__ dbeta,
                       float* __restrict__ dg, Gdn2 gd) {
@@ -972,10 +973,18 @@ __global__ void __launch_bounds__(CT, 1)
                 __syncthreads();
                 float off = 0.f;   // sum of the later segments
                 for (int s2 = seg + 1; s2 < 4; ++s2) off += sSeg[s2 * D + col];
+                if (n == BT) {
+                    // a full chunk: dg as a dense [64][128] fp32 tile over the spent dk array, written
+                    // by one TMA store after the unit's last barrier (the load/store pipe stays free)
+                    float* stg = reinterpret_cast<float*>(base + X_FD);
 #pragma unroll
-                for (int r = 0; r < 16; ++r) {
-                    const int row = 16 * seg + r;
-                    if (row < n) dg[((size_t)(tok0 + row) * H + h) * D + col] = x[r] + off;
+                    for (int r = 0; r < 16; ++r) stg[(16 * seg + r) * D + col] = x[r] + off;
+                } else {
+#pragma unroll
+                    for (int r = 0; r < 16; ++r) {
+                        const int row = 16 * seg + r;
+                        if (row < n) dg[((size_t)(tok0 + row) * H + h) * D + col] = x[r] + off;
+                    }
                 }
             } else {
                 for (int r = warp; r < BT; r += CT / 32) {
@@ -1000,6 +1009,11 @@ __global__ void __launch_bounds__(CT, 1)
         tc::fence_before_sync();
         __syncthreads();
         if (tid == LDR) {
+            if (GATE == 2 && n == BT) {   // dg of a full chunk from its staging tile; read before X2 lands
+                tc::tma_store3(&tmdg, 0, h, tok0, sb + X_FD);
+                tc::bulk_commit();
+                tc::bulk_wait_read();
+            }
             const int* nm = sMeta + 4 * ((k + 1) & 1);
             if (nm[0] >= 0) {
                 cons_load_x2(sb, &tmo, &tmv, bw, (size_t)nm[0], nm[0] % H, nm[2], bldX2);
@@ -1007,8 +1021,10 @@ __global__ void __launch_bounds__(CT, 1)
             }
         }
     }
-    // a load still in flight (only after a timeout) lands before the CTA leaves
+    // a load still in flight (only after a timeout) lands before the CTA leaves; the last dg store
+    // completes
     if (tid == LDR) {
+        tc::bulk_wait_all();
         for (; wC < nC; ++wC) tc::mbar_wait(bldC, wC & 1);
         for (; wX1 < nX1; ++wX1) tc::mbar_wait(bldX1, wX1 & 1);
         for (; wX2 < nX2; ++wX2) tc::mbar_wait(bldX2, wX2 & 1);
@@ -1024,16 +1040,17 @@ cudaError_t run_consumer(const Shape& s, const void* q, const void* k, const voi
                          void* dv, void* dbeta, float* dg, cudaStream_t st, const Gdn2& gd) {
     cudaError_t e = set_smem_once<k_bwd_consumer_tc<GATE, GD2>>(CONS_SMEM);
     if (e != cudaSuccess) return e;
-    CUtensorMap mq, mk, mo, mg, mv;
+    CUtensorMap mq, mk, mo, mg, mv, mdg;
     memset(&mg, 0, sizeof(mg));
+    memset(&mdg, 0, sizeof(mdg));
     if (!tmap_rows_bf16(&mq, q, s.Ttot, s.H, D) || !tmap_rows_bf16(&mk, k, s.Ttot, s.H, D) ||
         !tmap_rows_bf16(&mo, dout, s.Ttot, s.H, D) || !tmap_rows_bf16(&mv, v, s.Ttot, s.H, D) ||
-        (GATE == 2 && !tmap_rows_f32(&mg, g, s.Ttot, s.H, D)))
+        (GATE == 2 && (!tmap_rows_f32(&mg, g, s.Ttot, s.H, D) || !tmap_rows_f32(&mdg, dg, s.Ttot, s.H, D))))
         return cudaErrorInvalidValue;
     const long units = (long)s.NC * s.H;
     if (units <= 0) return cudaSuccess;
     const int grid = (int)(units < sm_count() ? units : sm_count());   // one CTA per SM, persistent
-    k_bwd_consumer_tc<GATE, GD2><<<grid, CT, CONS_SMEM, st>>>(s, mq, mk, mo, mg, mv, (const bf16*)beta, g, t, f, b,
+    k_bwd_consumer_tc<GATE, GD2><<<grid, CT, CONS_SMEM, st>>>(s, mq, mk, mo, mg, mv, mdg, (const bf16*)beta, g, t, f, b,
                                                          (bf16*)dq, (bf16*)dk, (bf16*)dv, (bf16*)dbeta, dg, gd);
     return cudaGetLastError();
 }
