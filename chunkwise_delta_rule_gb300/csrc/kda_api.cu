@@ -28,7 +28,8 @@ kda_status check_dims(const kda_problem* p, Dims& d) {
     if (!p) return fail(KDA_ERR_INVALID_ARG, "problem is NULL");
     if (p->B < 1 || p->T < 0 || p->H < 1 || p->K < 1 || p->V < 1)
         return fail(KDA_ERR_INVALID_ARG, "B, H, K, V must be >= 1 and T >= 0");
-    if (p->K > 128 || p->V > 128) return fail(KDA_ERR_UNSUPPORTED, "key or value width above 128 is not built");
+    if (p->K > 128) return fail(KDA_ERR_UNSUPPORTED, "key width above 128 is not built");
+    if (p->V > 4096) return fail(KDA_ERR_UNSUPPORTED, "value width above 4096");
     if (p->H > 65535) return fail(KDA_ERR_UNSUPPORTED, "H > 65535");
     if (p->io != KDA_BF16 && p->io != KDA_FP32) return fail(KDA_ERR_INVALID_ARG, "unknown io dtype");
     if (p->gate != KDA_GATE_NONE && p->gate != KDA_GATE_SCALAR && p->gate != KDA_GATE_CHANNEL)
@@ -38,6 +39,8 @@ kda_status check_dims(const kda_problem* p, Dims& d) {
     if (p->qk_l2norm != 0 && p->qk_l2norm != 1) return fail(KDA_ERR_INVALID_ARG, "qk_l2norm must be 0 or 1");
     if (p->HV != 0 && p->HV != p->H && (p->HV < p->H || p->HV % p->H != 0 || p->HV > 65535))
         return fail(KDA_ERR_INVALID_ARG, "HV must be 0 or a multiple of H (at most 65535)");
+    if ((long long)(p->HV ? p->HV : p->H) * ((p->V + 127) / 128) > 65535)
+        return fail(KDA_ERR_UNSUPPORTED, "value heads times value blocks of 128 above 65535");
     if ((p->erase == nullptr) != (p->write == nullptr))
         return fail(KDA_ERR_INVALID_ARG, "erase and write come together (GatedDeltaNet-2)");
     if (p->A_log && p->gate == KDA_GATE_NONE) return fail(KDA_ERR_INVALID_ARG, "A_log needs a gate");
@@ -273,6 +276,78 @@ size_t gva_bytes(const kda_problem* p, const Dims& d, bool bwd) {
     return one * (bwd ? 4 : 2);   // q, k copies (and, backward, their gradients)
 }
 
+// Value widths above 128: NB = ceil(V / 128) value blocks of width Vb = ceil(V / NB), each run
+// as a value head of its own (the state's value columns evolve independently). Value rows are
+// viewed as [tokens][value heads * NB][Vb] in place when NB * Vb == V, else padded first;
+// per-head inputs repeat per block and their gradients sum over the blocks.
+int vblocks(const kda_problem* p) { return p->V > 128 ? (p->V + 127) / 128 : 1; }
+int vblock_width(const kda_problem* p) { return (p->V + vblocks(p) - 1) / vblocks(p); }
+bool vsplit(const kda_problem* p) { return vblocks(p) > 1; }
+long long heads_v(const kda_problem* p) { return p->HV ? p->HV : p->H; }
+// channels of g (and dt_bias) per token and head
+int gate_width(const kda_problem* p) { return p->gate == KDA_GATE_NONE ? 0 : (p->gate == KDA_GATE_CHANNEL ? p->K : 1); }
+struct SplitBufs {
+    void *v = nullptr, *write = nullptr, *o = nullptr, *dout = nullptr, *dv = nullptr, *dwrite = nullptr;   // padded
+    void *beta = nullptr, *erase = nullptr, *dbeta = nullptr, *derase = nullptr;   // per block
+    float *g = nullptr, *A_log = nullptr, *dtb = nullptr, *dg = nullptr, *dA = nullptr, *ddtb = nullptr;
+    float *h0 = nullptr, *ht = nullptr, *dht = nullptr, *dh0 = nullptr;   // [N][value heads * NB][K][Vb]
+};
+size_t split_layout(const kda_problem* p, const Dims& d, bool bwd, char* base, SplitBufs& b) {
+    const size_t NB = vblocks(p), Vp = NB * vblock_width(p), es = p->io == KDA_BF16 ? 2 : 4;
+    const size_t Hv = heads_v(p), T = d.Ttot, N = d.N, K = p->K, gw = gate_width(p);
+    const bool padv = Vp != (size_t)p->V, gd2 = p->erase != nullptr;
+    size_t n = 0;
+    auto take = [&](size_t bytes) -> char* {
+        char* r = base ? base + n : nullptr;
+        n += up(bytes);
+        return r;
+    };
+    if (padv) {
+        b.v = take(es * T * Hv * Vp);
+        if (gd2) b.write = take(es * T * Hv * Vp);
+        b.o = take(es * T * Hv * Vp);
+    }
+    if (!gd2) b.beta = take(es * T * Hv * NB);
+    if (gd2) b.erase = take(es * T * Hv * NB * K);
+    if (gw) b.g = reinterpret_cast<float*>(take(4 * T * Hv * NB * gw));
+    if (p->A_log) b.A_log = reinterpret_cast<float*>(take(4 * Hv * NB));
+    if (p->dt_bias) b.dtb = reinterpret_cast<float*>(take(4 * Hv * NB * gw));
+    if (p->h0) b.h0 = reinterpret_cast<float*>(take(4 * N * Hv * K * Vp));
+    b.ht = reinterpret_cast<float*>(take(4 * N * Hv * K * Vp));
+    if (bwd) {
+        if (padv) {
+            b.dout = take(es * T * Hv * Vp);
+            b.dv = take(es * T * Hv * Vp);
+            if (gd2) b.dwrite = take(es * T * Hv * Vp);
+        }
+        if (!gd2) b.dbeta = take(es * T * Hv * NB);
+        if (gd2) b.derase = take(es * T * Hv * NB * K);
+        if (gw) b.dg = reinterpret_cast<float*>(take(4 * T * Hv * NB * gw));
+        if (p->A_log) b.dA = reinterpret_cast<float*>(take(4 * Hv * NB));
+        if (p->dt_bias) b.ddtb = reinterpret_cast<float*>(take(4 * Hv * NB * gw));
+        b.dht = reinterpret_cast<float*>(take(4 * N * Hv * K * Vp));
+        b.dh0 = reinterpret_cast<float*>(take(4 * N * Hv * K * Vp));
+    }
+    return n;
+}
+// The value-block problem (sizes only, or pointed at the split buffers).
+kda_problem split_inner(const kda_problem* p, const SplitBufs* b) {
+    kda_problem c = *p;
+    c.V = vblock_width(p);
+    c.HV = (int)(heads_v(p) * vblocks(p));
+    if (b) {
+        if (b->v) c.v = b->v;
+        if (b->write) c.write = b->write;
+        if (b->beta) c.beta = b->beta;
+        if (b->erase) c.erase = b->erase;
+        if (b->g) c.g = b->g;
+        if (b->A_log) c.A_log = b->A_log;
+        if (b->dtb) c.dt_bias = b->dtb;
+        c.h0 = b->h0;
+    }
+    return c;
+}
+
 // The optional prologue (normalised q, k; activated decay) and what it needs.
 bool has_prologue(const kda_problem* p) { return p->A_log || p->qk_l2norm; }
 float l2eps(const kda_problem* p) { return p->l2norm_eps > 0.f ? p->l2norm_eps : 1e-6f; }
@@ -432,6 +507,11 @@ size_t kda_workspace_size(const kda_problem* p, int for_backward) {
     Dims d;
     if (check_dims(p, d) != KDA_OK) return 0;
     if (d.Ttot == 0) return 0;
+    if (vsplit(p)) {
+        SplitBufs b;
+        const kda_problem in = split_inner(p, nullptr);
+        return kda_workspace_size(&in, for_backward) + split_layout(p, d, for_backward != 0, nullptr, b);
+    }
     if (pad_width(p)) {
         PadBufs b;
         const kda_problem in = pad_inner(p, nullptr);
@@ -448,6 +528,10 @@ size_t kda_workspace_size(const kda_problem* p, int for_backward) {
 size_t kda_saved_size(const kda_problem* p) {
     Dims d;
     if (check_dims(p, d) != KDA_OK) return 0;
+    if (vsplit(p) && d.Ttot > 0) {
+        const kda_problem in = split_inner(p, nullptr);
+        return kda_saved_size(&in);
+    }
     if (pad_width(p)) {
         const kda_problem in = pad_inner(p, nullptr);
         return kda_saved_size(&in);
@@ -833,8 +917,8 @@ static kda_status pad_inputs(const kda_problem* p, const Dims& d, const PadBufs&
     return io.e == cudaSuccess ? KDA_OK : cuda_fail(io.e, "pad to the working width");
 }
 
-kda_status kda_chunk_fwd(const kda_problem* p, void* o, float* ht, void* saved, void* ws, size_t ws_bytes,
-                         kda_stream_t stream) {
+static kda_status chunk_fwd_pad(const kda_problem* p, void* o, float* ht, void* saved, void* ws, size_t ws_bytes,
+                                kda_stream_t stream) {
     if (!p || !pad_width(p)) return chunk_fwd_gva(p, o, ht, saved, ws, ws_bytes, stream);
     Dims d;
     kda_status st = check_dims(p, d);
@@ -862,9 +946,10 @@ kda_status kda_chunk_fwd(const kda_problem* p, void* o, float* ht, void* saved, 
     return io.e == cudaSuccess ? KDA_OK : cuda_fail(io.e, "crop from the working width");
 }
 
-kda_status kda_chunk_bwd(const kda_problem* p, const void* dout, const float* dht, const void* saved, void* dq,
-                         void* dk, void* dv, float* dg, void* dbeta, void* derase, void* dwrite, float* dh0,
-                         float* dA_log, float* ddt_bias, void* ws, size_t ws_bytes, kda_stream_t stream) {
+static kda_status chunk_bwd_pad(const kda_problem* p, const void* dout, const float* dht, const void* saved,
+                                void* dq, void* dk, void* dv, float* dg, void* dbeta, void* derase, void* dwrite,
+                                float* dh0, float* dA_log, float* ddt_bias, void* ws, size_t ws_bytes,
+                                kda_stream_t stream) {
     if (!p || !pad_width(p))
         return chunk_bwd_gva(p, dout, dht, saved, dq, dk, dv, dg, dbeta, derase, dwrite, dh0, dA_log, ddt_bias, ws,
                              ws_bytes, stream);
@@ -910,6 +995,127 @@ kda_status kda_chunk_bwd(const kda_problem* p, const void* dout, const float* dh
     io.states(false, b.dh0, dh0);
     if (b.ddtb) io.rows(false, 4, Hv, p->K, b.ddtb, ddt_bias);
     return io.e == cudaSuccess ? KDA_OK : cuda_fail(io.e, "crop from the working width");
+}
+
+// Value widths above 128: the value-block problem after the inner problem's workspace.
+struct SplitIo {
+    const kda_problem* p;
+    const Dims& d;
+    cudaStream_t cs;
+    cudaError_t e = cudaSuccess;
+    int NB() const { return vblocks(p); }
+    int Vb() const { return vblock_width(p); }
+    int Vp() const { return NB() * Vb(); }
+    long long rows() const { return (long long)d.Ttot * heads_v(p); }
+    // value rows [rows][V] <-> [rows][NB * Vb]
+    void value_rows(bool pad, int es, const void* src, void* dst) {
+        if (e == cudaSuccess && src && dst)
+            e = traced(pad ? "k_pad" : "k_crop", cs,
+                       [&] { return kda::launch_pad(pad, es, rows(), 1, p->V, 1, Vp(), src, dst, cs); });
+    }
+    // per-head rows [M][W] -> [M][NB][W]
+    void repeat(int es, long long M, int W, const void* src, void* dst) {
+        if (e == cudaSuccess && src && dst)
+            e = traced("k_vblock_repeat", cs, [&] { return kda::launch_vblock_repeat(es, M, NB(), W, src, dst, cs); });
+    }
+    // gradients [M][NB][W] -> [M][W]
+    void sum(int es, long long M, int W, const void* src, void* dst) {
+        if (e == cudaSuccess && src && dst)
+            e = traced("k_vblock_sum", cs, [&] { return kda::launch_vblock_sum(es, M, NB(), W, src, dst, cs); });
+    }
+    // states [N * Hv][K][V] <-> [N * Hv][NB][K][Vb]
+    void states(bool split, const float* src, float* dst) {
+        if (e == cudaSuccess && src && dst)
+            e = traced("k_vblock_state", cs, [&] {
+                return kda::launch_vblock_state(split, (long long)d.N * heads_v(p), p->K, p->V, NB(), Vb(), src, dst, cs);
+            });
+    }
+};
+
+static kda_status split_inputs(const kda_problem* p, const Dims& d, const SplitBufs& b, cudaStream_t cs) {
+    SplitIo io{p, d, cs};
+    const int es = p->io == KDA_BF16 ? 2 : 4, gw = gate_width(p);
+    const long long Hv = heads_v(p);
+    io.value_rows(true, es, p->v, b.v);
+    io.value_rows(true, es, p->write, b.write);
+    io.repeat(es, io.rows(), 1, p->beta, b.beta);
+    io.repeat(es, io.rows(), p->K, p->erase, b.erase);
+    io.repeat(4, io.rows(), gw, p->g, b.g);
+    io.repeat(4, Hv, 1, p->A_log, b.A_log);
+    io.repeat(4, Hv, gw, p->dt_bias, b.dtb);
+    io.states(true, p->h0, b.h0);
+    return io.e == cudaSuccess ? KDA_OK : cuda_fail(io.e, "split into value blocks");
+}
+
+kda_status kda_chunk_fwd(const kda_problem* p, void* o, float* ht, void* saved, void* ws, size_t ws_bytes,
+                         kda_stream_t stream) {
+    if (!p || !vsplit(p)) return chunk_fwd_pad(p, o, ht, saved, ws, ws_bytes, stream);
+    Dims d;
+    kda_status st = check_dims(p, d);
+    if (st != KDA_OK) return st;
+    if ((st = check_inputs(p, d)) != KDA_OK) return st;
+    if (d.Ttot == 0) return chunk_fwd_pad(p, o, ht, saved, ws, ws_bytes, stream);   // ht = h0, no kernel
+    if (!o) return fail(KDA_ERR_INVALID_ARG, "o must be non-NULL");
+    const kda_problem in0 = split_inner(p, nullptr);
+    const size_t core = kda_workspace_size(&in0, 0);
+    SplitBufs b;
+    if ((st = check_ws(ws, ws_bytes, core + split_layout(p, d, false, nullptr, b))) != KDA_OK) return st;
+    split_layout(p, d, false, static_cast<char*>(ws) + core, b);
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    if ((st = split_inputs(p, d, b, cs)) != KDA_OK) return st;
+    const kda_problem in = split_inner(p, &b);
+    if ((st = chunk_fwd_pad(&in, b.o ? b.o : o, b.ht, saved, ws, core, stream)) != KDA_OK) return st;
+    SplitIo io{p, d, cs};
+    io.value_rows(false, p->io == KDA_BF16 ? 2 : 4, b.o, o);
+    io.states(false, b.ht, ht);
+    return io.e == cudaSuccess ? KDA_OK : cuda_fail(io.e, "merge the value blocks");
+}
+
+kda_status kda_chunk_bwd(const kda_problem* p, const void* dout, const float* dht, const void* saved, void* dq,
+                         void* dk, void* dv, float* dg, void* dbeta, void* derase, void* dwrite, float* dh0,
+                         float* dA_log, float* ddt_bias, void* ws, size_t ws_bytes, kda_stream_t stream) {
+    if (!p || !vsplit(p))
+        return chunk_bwd_pad(p, dout, dht, saved, dq, dk, dv, dg, dbeta, derase, dwrite, dh0, dA_log, ddt_bias, ws,
+                             ws_bytes, stream);
+    Dims d;
+    kda_status st = check_dims(p, d);
+    if (st != KDA_OK) return st;
+    if ((st = check_inputs(p, d)) != KDA_OK) return st;
+    if (d.Ttot == 0)   // dh0 = dht and zero parameter gradients, no kernel
+        return chunk_bwd_pad(p, dout, dht, saved, dq, dk, dv, dg, dbeta, derase, dwrite, dh0, dA_log, ddt_bias, ws,
+                             ws_bytes, stream);
+    if (!dout || !dq || !dk || !dv || (!p->erase && !dbeta))
+        return fail(KDA_ERR_INVALID_ARG, "dout, dq, dk, dv and dbeta must be non-NULL");
+    if (p->erase && (!derase || !dwrite))
+        return fail(KDA_ERR_INVALID_ARG, "derase and dwrite must be non-NULL with erase and write");
+    if ((p->gate == KDA_GATE_NONE) != (dg == nullptr))
+        return fail(KDA_ERR_INVALID_ARG, "dg must be non-NULL exactly when there is a gate");
+    const kda_problem in0 = split_inner(p, nullptr);
+    const size_t core = kda_workspace_size(&in0, 1);
+    SplitBufs b;
+    if ((st = check_ws(ws, ws_bytes, core + split_layout(p, d, true, nullptr, b))) != KDA_OK) return st;
+    split_layout(p, d, true, static_cast<char*>(ws) + core, b);
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    if ((st = split_inputs(p, d, b, cs)) != KDA_OK) return st;
+    SplitIo io{p, d, cs};
+    const int es = p->io == KDA_BF16 ? 2 : 4, gw = gate_width(p);
+    io.value_rows(true, es, dout, b.dout);
+    io.states(true, dht, b.dht);
+    if (io.e != cudaSuccess) return cuda_fail(io.e, "split into value blocks");
+    const kda_problem in = split_inner(p, &b);
+    st = chunk_bwd_pad(&in, b.dout ? b.dout : dout, dht ? b.dht : nullptr, saved, dq, dk, b.dv ? b.dv : dv, b.dg,
+                       b.dbeta, b.derase, b.dwrite ? b.dwrite : dwrite, b.dh0, b.dA, b.ddtb, ws, core, stream);
+    if (st != KDA_OK) return st;
+    const long long Hv = heads_v(p);
+    io.value_rows(false, es, b.dv, dv);
+    io.value_rows(false, es, b.dwrite, dwrite);
+    io.sum(4, io.rows(), gw, b.dg, dg);
+    io.sum(es, io.rows(), 1, b.dbeta, dbeta);
+    io.sum(es, io.rows(), p->K, b.derase, derase);
+    io.sum(4, Hv, 1, b.dA, dA_log);
+    io.sum(4, Hv, gw, b.ddtb, ddt_bias);
+    io.states(false, b.dh0, dh0);
+    return io.e == cudaSuccess ? KDA_OK : cuda_fail(io.e, "merge the value blocks");
 }
 
 kda_status kda_recurrent_fwd(const kda_problem* p, void* o, float* ht, int32_t* err, kda_stream_t stream) {

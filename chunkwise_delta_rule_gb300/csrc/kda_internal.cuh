@@ -229,6 +229,13 @@ cudaError_t launch_gva_expand(int Ttot, int HV, int G, int K, int bf16, const vo
                               cudaStream_t st);
 cudaError_t launch_gva_reduce(int Ttot, int H, int G, int K, int bf16, const void* dqx, const void* dkx, void* dq, void* dk,
                               cudaStream_t st);
+// Value blocks (value widths above 128): es is the element size in bytes (2: bf16, 4: fp32).
+// repeat: [M][W] -> [M][NB][W]; sum: [M][NB][W] -> [M][W]; state split: [M][K][V] ->
+// [M][NB][K][Vb] zero past column V, merge the reverse.
+cudaError_t launch_vblock_repeat(int es, long long M, int NB, int W, const void* src, void* dst, cudaStream_t st);
+cudaError_t launch_vblock_sum(int es, long long M, int NB, int W, const void* src, void* dst, cudaStream_t st);
+cudaError_t launch_vblock_state(bool split, long long M, int K, int V, int NB, int Vb, const float* src, float* dst,
+                                cudaStream_t st);
 // token-by-token forward (kda_recurrent.cu); T = tokens per sequence when cu is NULL
 cudaError_t launch_recurrent(const Shape& s, int bf16, int gate, int T, const int32_t* cu, const void* q,
                              const void* k, const void* v, const void* beta, const float* g, const float* h0,

@@ -91,7 +91,7 @@ def test_workspace_size_arithmetic():
 
 @pytest.mark.parametrize("kw,status", [
     (dict(K=192, V=192), 2),
-    (dict(K=128, V=160), 2),
+    (dict(K=160, V=128), 2),
     (dict(B=0), 1),
     (dict(gate=7), 1),
     (dict(io=5), 1),
@@ -209,3 +209,48 @@ def test_unequal_widths_pad_to_the_working_width():
     assert _ws(small, 0) > 0
     z = ctypes.c_void_p(0x3000)
     assert lib.kda_recurrent_fwd(ctypes.byref(p), z, None, None, None) == 2
+
+
+def test_wide_values_run_as_value_blocks():
+    def up(x):
+        return (x + 255) // 256 * 256
+
+    lib = _lib.load()
+    z = ctypes.c_void_p(0x3000)
+    # K = 128, V = 256: two value blocks of 128, each a value head of its own (HV = 2 H)
+    p = _prob(V=256)                    # bf16, channel gate, B=2, T=130, H=3, no h0
+    inner = _prob(V=128)
+    inner.HV = 6
+    T, Hv, K, NB = 2 * 130, 3, 128, 2
+    # beta and g repeated per block, the blocks' final states
+    split_f = up(2 * T * Hv * NB) + up(4 * T * Hv * NB * K) + up(4 * 2 * Hv * K * 256)
+    assert _ws(p, 0) == _ws(inner, 0) + split_f
+    # backward adds the blocks' dbeta, dg, dht and dh0
+    split_b = split_f + up(2 * T * Hv * NB) + up(4 * T * Hv * NB * K) + 2 * up(4 * 2 * Hv * K * 256)
+    assert _ws(p, 1) == _ws(inner, 1) + split_b
+    assert lib.kda_saved_size(ctypes.byref(_prob(V=256, save=1))) == \
+        lib.kda_saved_size(ctypes.byref(_set(_prob(V=128, save=1), HV=6)))
+    # V = 201: two blocks of 101, value rows padded to 202 (v and o in the forward)
+    odd = _prob(V=201, gate=1)
+    inner = _set(_prob(V=101, gate=1), HV=6)
+    rows = up(2 * T * Hv * 202)
+    split_f = 2 * rows + up(2 * T * Hv * NB) + up(4 * T * Hv * NB) + up(4 * 2 * Hv * K * 202)
+    assert _ws(odd, 0) == _ws(inner, 0) + split_f
+    # limits: key width above 128; value width above 4096; value heads x blocks above 65535
+    for kw, fld in ((dict(K=192), None), (dict(V=4097), None), (dict(H=30000, V=384), None)):
+        q = _prob(**kw)
+        assert lib.kda_chunk_fwd(ctypes.byref(q), z, None, None, None, 0, None) == 2
+        assert _ws(q, 0) == 0
+    # the token-by-token forward stays at K = V = 64 or 128
+    assert lib.kda_recurrent_fwd(ctypes.byref(_prob(V=256)), z, None, None, None) == 2
+    # the backward's argument checks come before any launch
+    p = _prob(V=256)
+    assert lib.kda_chunk_bwd(ctypes.byref(p), z, None, None, z, z, z, z, None, None, None, None, None, None,
+                             z, 1 << 40, None) == 1
+    assert "dbeta" in _lib.last_error()
+
+
+def _set(p, **kw):
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p

@@ -1,7 +1,8 @@
 """GPU parity at key and value widths other than K = V = 64 or 128 (served
-zero-padded to the working width and cropped back), alone and together with
-grouped value heads, the GatedDeltaNet-2 vectors and the prologue, against
-the FP64 oracle at the true widths."""
+zero-padded to the working width and cropped back; value widths above 128 as
+value blocks, each a value head of its own), alone and together with grouped
+value heads, the GatedDeltaNet-2 vectors and the prologue, against the FP64
+oracle at the true widths."""
 
 import numpy as np
 import pytest
@@ -91,3 +92,35 @@ def test_widths_with_grouped_heads_gdn2_and_prologue():
     case = width_case("bf16", "channel", 1, 90, 4, 96, 80, 102)
     got, ref = run_both(case, G=2, gdn2=True, prologue=True)
     compare(case, got, ref, 2, TOL["bf16"])
+
+
+# value widths above 128: NB = ceil(V / 128) blocks of ceil(V / NB) columns; 256 runs as two
+# 128-wide blocks on the tensor-core path, 201 as two blocks of 101 with the value rows padded
+@pytest.mark.parametrize("io,gate,K,V", [("bf16", "channel", 128, 256), ("fp32", "scalar", 64, 201),
+                                         ("bf16", "none", 96, 160), ("fp32", "channel", 128, 384)])
+def test_wide_values_match_oracle(io, gate, K, V):
+    case = width_case(io, gate, 2, 100, 2, K, V, 103)
+    got, ref = run_both(case)
+    compare(case, got, ref, 1, TOL[io])
+
+
+def test_wide_values_with_grouped_heads_gdn2_and_prologue():
+    case = width_case("bf16", "channel", 1, 90, 4, 128, 192, 104)
+    got, ref = run_both(case, G=2, gdn2=True, prologue=True)
+    compare(case, got, ref, 2, TOL["bf16"])
+
+
+def test_wide_values_saved_equals_recomputed():
+    import chunkwise_delta_rule_gb300 as kda
+    case = width_case("bf16", "channel", 1, 150, 2, 128, 256, 105)
+    c = case.to("cuda")
+    out = []
+    for policy in (0, 1):
+        p = kda.make_problem(c.q, c.k, c.v, c.g, c.beta, gate="channel", scale=case.scale, initial_state=c.h0,
+                             save_policy=policy)
+        o, ht, sv = kda.kda_chunk_fwd(p)
+        out.append((o, ht) + tuple(kda.kda_chunk_bwd(p, c.do, c.dht, saved=sv)))
+    torch.cuda.synchronize()
+    for a, b in zip(*out):
+        if a is not None:
+            assert torch.equal(a, b)

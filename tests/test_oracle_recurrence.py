@@ -256,3 +256,27 @@ def test_split_call_equals_one_call():
     for key in ("dq", "dk", "dv", "dbeta", "dg"):
         np.testing.assert_allclose(np.concatenate([ra[key], rb[key]]), full[key], rtol=1e-11, atol=1e-12)
     np.testing.assert_allclose(ra["dh0"], full["dh0"], rtol=1e-11, atol=1e-12)
+
+
+@pytest.mark.parametrize("gate", ["channel", "scalar", "none"])
+def test_value_columns_are_independent_subproblems(gate):
+    """The delta-rule update acts on each value column of the state on its own
+    ("ReWY" paper, the state recurrence): splitting v, h0, do and dht into
+    value blocks gives o, ht, dv, dh0 as the blocks' results side by side and
+    dq, dk, dbeta, dg as the sums of the blocks' ones (the loss is the sum of
+    the blocks' losses). This is what lets value widths above the kernels'
+    tile run as value blocks."""
+    rng = np.random.default_rng(17)
+    d = _rand(rng, [70, 9], 2, 6, 11, gate)
+    full = _run(d, gate, 0.5)
+    cuts = [0, 4, 11]
+    parts = []
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        blk = dict(d, v=d["v"][..., a:b], do=d["do"][..., a:b], h0=d["h0"][..., a:b], dht=d["dht"][..., a:b])
+        parts.append(_run(blk, gate, 0.5))
+    for key in ("o", "ht", "dv", "dh0"):
+        np.testing.assert_allclose(np.concatenate([p[key] for p in parts], axis=-1), full[key],
+                                   rtol=1e-12, atol=1e-13)
+    keys = ("dq", "dk", "dbeta") + (("dg",) if gate != "none" else ())
+    for key in keys:
+        np.testing.assert_allclose(sum(p[key] for p in parts), full[key], rtol=1e-10, atol=1e-12)
