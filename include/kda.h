@@ -47,7 +47,7 @@ typedef struct CUstream_st *kda_stream_t;
 typedef enum {
     KDA_OK = 0,
     KDA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, inconsistent fields */
-    KDA_ERR_UNSUPPORTED = 2,   /* valid but not built (e.g. K != V, K = 96) */
+    KDA_ERR_UNSUPPORTED = 2,   /* valid but not built (e.g. K above 128) */
     KDA_ERR_WORKSPACE = 3,     /* workspace or saved buffer too small / misaligned */
     KDA_ERR_CUDA = 4,          /* a launch or runtime call failed */
     KDA_ERR_DEVICE_TIMEOUT = 5 /* a bounded device wait gave up (kda_device_status) */
@@ -63,8 +63,13 @@ typedef enum { KDA_GATE_NONE = 0, KDA_GATE_SCALAR = 1, KDA_GATE_CHANNEL = 2 } kd
 
 typedef struct {
     int B, T, H, K, V;          /* batch, tokens per sequence (total tokens when packed),
-                                   heads, key width, value width (each 1..128; other than
-                                   K = V = 64 or 128 the chunked calls run zero-padded) */
+                                   heads, key width (1..128), value width (1..4096). Other
+                                   than K = V = 64 or 128 the chunked calls run zero-padded;
+                                   V above 128 runs as ceil(V / 128) value blocks, each a
+                                   value head of its own (the delta-rule update moves every
+                                   value column of the state independently, "ReWY" paper,
+                                   the state recurrence). The token-by-token call needs
+                                   K = V = 64 or 128. */
     int N;                      /* packed sequences (used only when cu_seqlens != NULL) */
     const int32_t *cu_seqlens;  /* device, N+1 non-decreasing token offsets, first 0,
                                    last B*T; NULL for equal-length sequences */
@@ -110,8 +115,8 @@ typedef struct {
 
 /* Bytes of device workspace kda_chunk_fwd (for_backward = 0) or kda_chunk_bwd
  * (for_backward = 1) needs for this problem; 0 if the problem is invalid.
- * Only the size fields, io, gate, cu_seqlens (null or not) and save_policy
- * are read. The workspace must be 256-byte aligned; its contents need no
+ * Only the size fields, io, gate, save_policy, qk_l2norm and whether
+ * cu_seqlens, h0, A_log, dt_bias and erase are set are read. The workspace must be 256-byte aligned; its contents need no
  * initialisation and are scratch after the call. */
 size_t kda_workspace_size(const kda_problem *p, int for_backward);
 
