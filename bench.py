@@ -434,48 +434,99 @@ def run_ours(args):
 
 def run_e2e(args, case_cpu, dev, kda, K):
     """Same metric through the public API with host buffers: every step copies
-    the inputs from pinned host memory, runs forward and backward, and reads
-    every output back to pinned host memory."""
+    every input from pinned host memory, runs forward and backward, and reads
+    every output back to pinned host memory. The batch runs as one piece per
+    sequence (packed sequences: one piece), pipelined over three streams
+    (inputs, compute, outputs) with double-buffered device inputs, so that one
+    piece's copies overlap another piece's compute and the two copy directions
+    overlap each other. The pieces' results are checked against one call on
+    the whole batch first."""
     import torch
     names = ["q", "k", "v", "g", "beta", "h0", "do", "dht"]
-    host = {n: getattr(case_cpu, n).pin_memory() for n in names if getattr(case_cpu, n) is not None}
-    if case_cpu.cu_seqlens is not None:
-        host["cu_seqlens"] = case_cpu.cu_seqlens.pin_memory()
-    devt = {n: torch.empty_like(t, device=dev) for n, t in host.items()}
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
-    outs_host = None
+    full = {n: getattr(case_cpu, n).pin_memory() for n in names if getattr(case_cpu, n) is not None}
+    P = case_cpu.B if case_cpu.cu_seqlens is None else 1
+    if P == 1:
+        host = [full]
+        if case_cpu.cu_seqlens is not None:
+            host[0]["cu_seqlens"] = case_cpu.cu_seqlens.pin_memory()
+    else:   # token tensors are [B, T, ...] and states [B, H, K, V]: sequence b is slice b
+        host = [{n: t[b:b + 1] for n, t in full.items()} for b in range(P)]
+    devt = [[{n: torch.empty_like(t, device=dev) for n, t in hp.items()} for hp in host] for _ in range(2)]
+    h2d = sum(t.numel() * t.element_size() for hp in host for t in hp.values())
+    s_in, s_cp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [[torch.cuda.Event() for _ in range(P)] for _ in range(2)]
+    ev_used = [[torch.cuda.Event() for _ in range(P)] for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(P)]
+    outs_host = [None] * P
     d2h = 0
+
+    def run(d):
+        p = kda.make_problem(d["q"], d["k"], d["v"], d.get("g"), d["beta"], gate=case_cpu.gate,
+                             scale=case_cpu.scale, initial_state=d.get("h0"), cu_seqlens=d.get("cu_seqlens"),
+                             save_policy=1 if args.policy == "save" else 0)
+        o, ht, sv = kda.kda_chunk_fwd(p)
+        grads = kda.kda_chunk_bwd(p, d["do"], d.get("dht"), saved=sv)
+        return [o, ht] + [x for x in grads if x is not None]
+
+    def step(st):
+        nonlocal d2h
+        buf = devt[st % 2]
+        for b in range(P):
+            with torch.cuda.stream(s_in):
+                s_in.wait_event(ev_used[st % 2][b])   # the compute that last read this buffer is done
+                for n, t in host[b].items():
+                    buf[b][n].copy_(t, non_blocking=True)
+                ev_in[st % 2][b].record(s_in)
+            with torch.cuda.stream(s_cp):
+                s_cp.wait_event(ev_in[st % 2][b])
+                res = run(buf[b])
+                ev_used[st % 2][b].record(s_cp)
+                ev_done[b].record(s_cp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_done[b])
+                if outs_host[b] is None:
+                    outs_host[b] = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in res]
+                    d2h += sum(x.numel() * x.element_size() for x in res)
+                for hbuf, x in zip(outs_host[b], res):
+                    hbuf.copy_(x, non_blocking=True)
+                    x.record_stream(s_out)
+
+    def join():
+        cur = torch.cuda.current_stream()
+        for sx in (s_in, s_cp, s_out):
+            cur.wait_stream(sx)
+
+    for st in range(2):
+        step(st)
+    join()
+    torch.cuda.synchronize()
+    # the pieces against one call on the whole batch (device-resident inputs)
+    ref = run({n: t.to(dev) for n, t in full.items()} | ({"cu_seqlens": host[0]["cu_seqlens"].to(dev)}
+                                                          if "cu_seqlens" in host[0] else {}))
+    torch.cuda.synchronize()
+    worst = 0.0
+    for b in range(P):
+        for hx, rx in zip(outs_host[b], ref):
+            r = rx.cpu() if P == 1 else rx[b:b + 1].cpu()
+            if not torch.equal(hx, r):
+                worst = max(worst, float((hx.double() - r.double()).abs().max()))
+    del ref
     s0 = torch.cuda.Event(enable_timing=True)
     s1 = torch.cuda.Event(enable_timing=True)
-
-    def one():
-        nonlocal outs_host, d2h
-        for n, t in host.items():
-            devt[n].copy_(t, non_blocking=True)
-        p = kda.make_problem(devt["q"], devt["k"], devt["v"], devt.get("g"), devt["beta"],
-                             gate=case_cpu.gate, scale=case_cpu.scale, initial_state=devt.get("h0"),
-                             cu_seqlens=devt.get("cu_seqlens"), save_policy=1 if args.policy == "save" else 0)
-        o, ht, sv = kda.kda_chunk_fwd(p)
-        grads = kda.kda_chunk_bwd(p, devt["do"], devt.get("dht"), saved=sv)
-        res = [o, ht] + [x for x in grads if x is not None]
-        if outs_host is None:
-            outs_host = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in res]
-            d2h = sum(x.numel() * x.element_size() for x in res)
-        for hbuf, x in zip(outs_host, res):
-            hbuf.copy_(x, non_blocking=True)
-
-    for _ in range(2):
-        one()
-    torch.cuda.synchronize()
     s0.record()
-    for _ in range(K):
-        one()
+    for sx in (s_in, s_cp, s_out):
+        sx.wait_event(s0)
+    for st in range(K):
+        step(st)
+    join()
     s1.record()
     torch.cuda.synchronize()
     ms = s0.elapsed_time(s1) / K
     tokens = case_cpu.B * case_cpu.T
     return {"value": round(tokens / (ms * 1e-3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
-            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "pipeline": f"{P} piece(s) (whole sequences), input/compute/output streams, double-buffered inputs",
+            "pieces_vs_whole_batch": "bitwise equal" if worst == 0.0 else f"max abs diff {worst:.3e}"}
 
 
 # ------------------------------------------------------ oracle (CPU) timing
