@@ -242,6 +242,25 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(x, ws, device):
+    """The largest x over all ranks (each rank passes its own step time); x itself
+    with one rank. Works on any initialised backend (device: where the reduced
+    tensor lives, a CUDA device for NCCL, the CPU for gloo)."""
+    if ws <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank, ws, step_ms):
+    """Weak scaling: every rank runs its own replica of the workload each step, so
+    the job's rate is the units of all ranks over the slowest rank's step time."""
+    return ws * units_per_rank / (step_ms * 1e-3)
+
+
 # ----------------------------------------------------------------- our arm
 def run_ours(args):
     import torch
@@ -336,15 +355,11 @@ def run_ours(args):
     fwd_ms = [a.elapsed_time(b) for a, b, _ in ev]
     bwd_ms = [b.elapsed_time(c) for _, b, c in ev]
     step_ms = sum(fwd_ms) / K + sum(bwd_ms) / K
-    if ws > 1:
-        import torch.distributed as dist
-        t = torch.tensor([step_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms = float(t.item())
+    step_ms = max_over_ranks(step_ms, ws, dev)
 
     tokens = case.B * case.T
     fl_f, fl_b, fl_r = flops_model(case)
-    value = ws * tokens / (step_ms * 1e-3)
+    value = whole_job_rate(tokens, ws, step_ms)
     tflops = ws * (fl_f + fl_b) / (step_ms * 1e-3) / 1e12
     tflops_exec = ws * (fl_f + fl_b + (fl_r if args.policy == "recompute" else 0.0)) / (step_ms * 1e-3) / 1e12
     pk = peaks()
