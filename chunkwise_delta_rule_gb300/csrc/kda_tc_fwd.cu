@@ -296,6 +296,21 @@ __global__ void __launch_bounds__(PT, 2)
             *reinterpret_cast<float4*>(alr + e) = *reinterpret_cast<const float4*>(sAL + c8 + e);
         }
         constexpr int NU = BT * D / 8 / PT;   // 16-byte chunks per thread
+        // GatedDeltaNet-2: the erase and write vectors of this thread's chunks, all read from HBM
+        // before the pass's first shared-memory store so that the loads overlap one another
+        uint4 er_all[GD2 ? NU : 1], wr_all[GD2 ? NU : 1];
+        if (GD2) {
+#pragma unroll
+            for (int u = 0; u < NU; ++u) {
+                const int i = (tid + PT * u) >> 4;
+                er_all[u] = wr_all[u] = make_uint4(0, 0, 0, 0);
+                if (i < n) {
+                    const size_t o = ((size_t)(tok0 + i) * H + h) * D + c8;
+                    er_all[u] = *reinterpret_cast<const uint4*>(static_cast<const bf16*>(gd.erase) + o);
+                    wr_all[u] = *reinterpret_cast<const uint4*>(static_cast<const bf16*>(gd.write) + o);
+                }
+            }
+        }
 #pragma unroll
         for (int u = 0; u < NU; ++u) {
             const int i = (tid + PT * u) >> 4;
@@ -306,12 +321,10 @@ __global__ void __launch_bounds__(PT, 2)
             const bf16* kv = reinterpret_cast<const bf16*>(&kr);
             const bf16* qv = reinterpret_cast<const bf16*>(&qr);
             // GatedDeltaNet-2: the erase vector on E's key rows in place of beta, and V scaled by
-            // the write vector in place (U = A (w .* V)); both read straight from HBM
-            uint4 er4 = make_uint4(0, 0, 0, 0);
+            // the write vector in place (U = A (w .* V))
+            const uint4 er4 = er_all[GD2 ? u : 0];
             if (GD2 && i < n) {
-                const size_t o = ((size_t)(tok0 + i) * H + h) * D + c8;
-                er4 = *reinterpret_cast<const uint4*>(static_cast<const bf16*>(gd.erase) + o);
-                const uint4 wr4 = *reinterpret_cast<const uint4*>(static_cast<const bf16*>(gd.write) + o);
+                const uint4 wr4 = wr_all[GD2 ? u : 0];
                 uint4* vp = reinterpret_cast<uint4*>(base + P_V + tc::sw128_off(BT, i, c8 * 2));
                 const uint4 v4 = *vp;
                 const bf16* vv = reinterpret_cast<const bf16*>(&v4);
