@@ -922,6 +922,12 @@ __global__ void __launch_bounds__(CT, 1)
                 // kept as bf16 so the load stays in flight until the next unit starts
                 if (tid < BT)
                     beta_nx = (tid < nm[1] && !GD2) ? beta[(size_t)(nm[2] + tid) * H + nh] : __float2bfloat16_rn(0.f);
+                // GatedDeltaNet-2: the next unit's erase and write rows (two 128-byte lines each)
+                // into L2, so that its direct loads of them find them there
+                if (GD2 && (tid >> 2) < nm[1]) {
+                    const bf16* vec = static_cast<const bf16*>((tid & 2) ? gd.write : gd.erase);
+                    tc::prefetch_l2(vec + ((size_t)(nm[2] + (tid >> 2)) * H + nh) * D + (tid & 1) * 64);
+                }
             }
         }
         // ---- F3: dk, dbeta; key rows add the erase part of G_bar; the endpoint terms of the last

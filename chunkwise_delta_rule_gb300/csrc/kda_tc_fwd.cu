@@ -214,6 +214,12 @@ __global__ void __launch_bounds__(PT, 2)
         if (GATE == 2) tc::tma_load3(sb + P_ALPHA, &tmg, 0, h, tok0, bld);
     }
     const float beta_r = (tid < BT && tid < n && !GD2) ? bfx(beta + (size_t)(tok0 + tid) * H + h) : 0.f;
+    // GatedDeltaNet-2: this chunk's erase and write rows (two 128-byte lines each) into L2 while
+    // the cumsum runs; the operand pass reads them
+    if (GD2 && (tid >> 2) < n) {
+        const bf16* vec = static_cast<const bf16*>((tid & 2) ? gd.write : gd.erase);
+        tc::prefetch_l2(vec + ((size_t)(tok0 + (tid >> 2)) * H + h) * D + (tid & 1) * 64);
+    }
     if (GATE != 2) {
         // scalar gate: the G tile repeats the token's log-decay; no gate: zeros
         for (int idx = tid; idx < BT * D / 4; idx += PT) {
