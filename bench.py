@@ -137,14 +137,20 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, dev_uuid=None):
+    def __init__(self, dev_uuid=None, path=None):
+        """path: where the raw samples go (kept); None: a temporary file, removed after parsing."""
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", "clocks.csv")
+        self.keep = bool(path)
+        if not path:
+            import tempfile
+            fd, path = tempfile.mkstemp(prefix="kda_clocks_", suffix=".csv")
+            os.close(fd)
+        self.path = path
         self.uuid = dev_uuid
 
     def start(self):
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            os.makedirs(os.path.dirname(os.path.abspath(self.path)), exist_ok=True)
             cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
                    "-lms", "200"]
             if self.uuid:
@@ -177,6 +183,11 @@ class ClockSampler:
             for nm, val in zip(names, parts[5:9]):
                 if val.lower() == "active":
                     reasons.add(nm)
+        if not self.keep:
+            try:
+                os.remove(self.path)
+            except OSError:
+                pass
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
@@ -329,7 +340,7 @@ def run_ours(args):
             uuid = "GPU-" + uuid
     except Exception:
         uuid = None
-    clocks = ClockSampler(uuid) if rank == 0 else None
+    clocks = ClockSampler(uuid, args.clocks_csv) if rank == 0 else None
     K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True)) for _ in range(K)]
@@ -626,7 +637,7 @@ def run_decode(args):
     torch.cuda.synchronize()
     K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    clocks = ClockSampler()
+    clocks = ClockSampler(None, args.clocks_csv)
     clocks.start()
     time.sleep(0.3)
     profile_begin(lib)
@@ -701,6 +712,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=WORKLOAD_IDX)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--clocks-csv", default="",
+                    help="keep the raw nvidia-smi clock samples of the timed region in this file")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--heads", type=int, default=0, help="restrict the workload to its first H heads (profiling)")
     ap.add_argument("--kv", default="", help="key,value widths (e.g. 80,112) for the same workload recipe")
