@@ -1124,7 +1124,8 @@ kda_status kda_recurrent_fwd(const kda_problem* p, void* o, float* ht, int32_t* 
     if (st != KDA_OK) return st;
     if ((st = check_inputs(p, d)) != KDA_OK) return st;
     if (p->save_policy != 0) return fail(KDA_ERR_INVALID_ARG, "the recurrent forward has no saved buffer: use save_policy 0");
-    if (pad_width(p)) return fail(KDA_ERR_UNSUPPORTED, "the token-by-token forward needs K = V = 64 or 128");
+    if ((p->K != 64 && p->K != 128) || p->V % 32 != 0)
+        return fail(KDA_ERR_UNSUPPORTED, "the token-by-token forward needs K = 64 or 128 and V a multiple of 32");
     if (d.Ttot > 0 && !o) return fail(KDA_ERR_INVALID_ARG, "o must be non-NULL");
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     const kda_problem in = gva(p) ? gva_inner(p, p->q, p->k) : *p;   // value heads; q, k read per group

@@ -69,7 +69,7 @@ typedef struct {
                                    value head of its own (the delta-rule update moves every
                                    value column of the state independently, "ReWY" paper,
                                    the state recurrence). The token-by-token call needs
-                                   K = V = 64 or 128. */
+                                   K = 64 or 128 and V a multiple of 32 (up to 4096). */
     int N;                      /* packed sequences (used only when cu_seqlens != NULL) */
     const int32_t *cu_seqlens;  /* device, N+1 non-decreasing token offsets, first 0,
                                    last B*T; NULL for equal-length sequences */

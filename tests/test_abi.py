@@ -241,8 +241,9 @@ def test_wide_values_run_as_value_blocks():
         q = _prob(**kw)
         assert lib.kda_chunk_fwd(ctypes.byref(q), z, None, None, None, 0, None) == 2
         assert _ws(q, 0) == 0
-    # the token-by-token forward stays at K = V = 64 or 128
-    assert lib.kda_recurrent_fwd(ctypes.byref(_prob(V=256)), z, None, None, None) == 2
+    # the token-by-token forward takes K = 64 or 128 and V a multiple of 32 (its CTAs own 32 columns)
+    assert lib.kda_recurrent_fwd(ctypes.byref(_prob(V=200)), z, None, None, None) == 2
+    assert lib.kda_recurrent_fwd(ctypes.byref(_prob(K=96, V=256)), z, None, None, None) == 2
     # the backward's argument checks come before any launch
     p = _prob(V=256)
     assert lib.kda_chunk_bwd(ctypes.byref(p), z, None, None, z, z, z, z, None, None, None, None, None, None,

@@ -20,8 +20,8 @@ pytestmark = pytest.mark.gpu
 TOL = {"fp32": 1e-4, "bf16": 2e-2}
 
 
-def gdn2_case(io, gate, B, T, H, K, seed, lengths=None):
-    case = make_case(io=io, gate=gate, B=B, T=T, H=H, K=K, V=K, seed=seed, lengths=lengths)
+def gdn2_case(io, gate, B, T, H, K, seed, lengths=None, V=None):
+    case = make_case(io=io, gate=gate, B=B, T=T, H=H, K=K, V=V or K, seed=seed, lengths=lengths)
     gen = torch.Generator().manual_seed(seed + 2000)
     dt = case.q.dtype
     b = (2.0 * torch.sigmoid(torch.randn(case.k.shape, generator=gen))).to(dt)
@@ -103,10 +103,10 @@ def test_gdn2_with_the_prologue():
     compare(case, gpu(case, b, w, prologue=pro), oracle(case, b, w, prologue=pro), TOL["fp32"])
 
 
-@pytest.mark.parametrize("io,K", [("fp32", 64), ("bf16", 128)])
-def test_gdn2_recurrent_matches_oracle(io, K):
+@pytest.mark.parametrize("io,K,V", [("fp32", 64, 64), ("bf16", 128, 128), ("bf16", 128, 256)])
+def test_gdn2_recurrent_matches_oracle(io, K, V):
     import chunkwise_delta_rule_gb300 as kda
-    case, b, w = gdn2_case(io, "channel", 2, 30, 2, K, 85)
+    case, b, w = gdn2_case(io, "channel", 2, 30, 2, K, 85, V=V)
     c = case.to("cuda")
     p = kda.make_problem(c.q, c.k, c.v, c.g, None, gate="channel", scale=case.scale, initial_state=c.h0,
                          erase=b.cuda(), write=w.cuda())

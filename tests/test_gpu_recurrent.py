@@ -44,10 +44,14 @@ CASES = [
     dict(io="bf16", gate="channel", B=2, T=64, H=2, K=128, V=128),
     dict(io="bf16", gate="scalar", B=1, T=33, H=2, K=64, V=64),
     dict(io="bf16", gate="none", B=2, T=5, H=2, K=128, V=128, h0=False),
+    # value widths other than K (any multiple of 32): Gated DeltaNet's V = 2K heads among them
+    dict(io="bf16", gate="scalar", B=2, T=9, H=2, K=128, V=256),
+    dict(io="fp32", gate="channel", B=1, T=20, H=3, K=64, V=96),
+    dict(io="bf16", gate="channel", B=2, T=3, H=2, K=128, V=32),
 ]
 
 
-@pytest.mark.parametrize("kw", CASES, ids=lambda kw: "{io}-{gate}-B{B}T{T}H{H}K{K}".format(**kw))
+@pytest.mark.parametrize("kw", CASES, ids=lambda kw: "{io}-{gate}-B{B}T{T}H{H}K{K}V{V}".format(**kw))
 def test_recurrent_matches_oracle(kw):
     case = make_case(seed=61, **kw)
     o, ht = rec_run(case)
