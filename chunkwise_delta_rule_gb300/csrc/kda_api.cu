@@ -23,12 +23,14 @@ struct Dims {
     int N = 0, NC = 0, Ttot = 0, D = 0, H = 0;
 };
 
-// Checks the size fields; fills d. Returns KDA_OK or an error (message set).
-kda_status check_dims(const kda_problem* p, Dims& d) {
+// Checks the size fields; fills d. Returns KDA_OK or an error (message set). The chunked calls
+// take key widths up to 128; the token-by-token call (chunked = false) checks its own.
+kda_status check_dims(const kda_problem* p, Dims& d, bool chunked = true) {
     if (!p) return fail(KDA_ERR_INVALID_ARG, "problem is NULL");
     if (p->B < 1 || p->T < 0 || p->H < 1 || p->K < 1 || p->V < 1)
         return fail(KDA_ERR_INVALID_ARG, "B, H, K, V must be >= 1 and T >= 0");
-    if (p->K > 128) return fail(KDA_ERR_UNSUPPORTED, "key width above 128 is not built");
+    if (chunked && p->K > 128) return fail(KDA_ERR_UNSUPPORTED, "chunked calls: key width above 128 is not built");
+    if (p->K > 256) return fail(KDA_ERR_UNSUPPORTED, "key width above 256");
     if (p->V > 4096) return fail(KDA_ERR_UNSUPPORTED, "value width above 4096");
     if (p->H > 65535) return fail(KDA_ERR_UNSUPPORTED, "H > 65535");
     if (p->io != KDA_BF16 && p->io != KDA_FP32) return fail(KDA_ERR_INVALID_ARG, "unknown io dtype");
@@ -1120,12 +1122,13 @@ kda_status kda_chunk_bwd(const kda_problem* p, const void* dout, const float* dh
 
 kda_status kda_recurrent_fwd(const kda_problem* p, void* o, float* ht, int32_t* err, kda_stream_t stream) {
     Dims d;
-    kda_status st = check_dims(p, d);
+    kda_status st = check_dims(p, d, false);
     if (st != KDA_OK) return st;
     if ((st = check_inputs(p, d)) != KDA_OK) return st;
     if (p->save_policy != 0) return fail(KDA_ERR_INVALID_ARG, "the recurrent forward has no saved buffer: use save_policy 0");
-    if ((p->K != 64 && p->K != 128) || p->V % 32 != 0)
-        return fail(KDA_ERR_UNSUPPORTED, "the token-by-token forward needs K = 64 or 128 and V a multiple of 32");
+    if (!kda::recurrent_key_width(p->K) || p->V % 32 != 0)
+        return fail(KDA_ERR_UNSUPPORTED,
+                    "the token-by-token forward needs K = 64, 128, 160, 192 or 256 and V a multiple of 32");
     if (d.Ttot > 0 && !o) return fail(KDA_ERR_INVALID_ARG, "o must be non-NULL");
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     const kda_problem in = gva(p) ? gva_inner(p, p->q, p->k) : *p;   // value heads; q, k read per group

@@ -236,7 +236,9 @@ cudaError_t launch_vblock_repeat(int es, long long M, int NB, int W, const void*
 cudaError_t launch_vblock_sum(int es, long long M, int NB, int W, const void* src, void* dst, cudaStream_t st);
 cudaError_t launch_vblock_state(bool split, long long M, int K, int V, int NB, int Vb, const float* src, float* dst,
                                 cudaStream_t st);
-// token-by-token forward (kda_recurrent.cu); T = tokens per sequence when cu is NULL
+// token-by-token forward (kda_recurrent.cu); T = tokens per sequence when cu is NULL. Key widths it
+// is built for (recurrent_key_width); V any multiple of 32.
+bool recurrent_key_width(int K);
 cudaError_t launch_recurrent(const Shape& s, int bf16, int gate, int T, const int32_t* cu, const void* q,
                              const void* k, const void* v, const void* beta, const float* g, const float* h0,
                              void* o, float* ht, int32_t* err, const float* A_log, const float* dt_bias,

@@ -246,18 +246,30 @@ cudaError_t run_recurrent_k(const Shape& s, int gate, const RecIO& io, cudaStrea
     return cudaGetLastError();
 }
 
+template <typename TI>
+cudaError_t run_recurrent_t(const Shape& s, int gate, const RecIO& io, cudaStream_t st) {
+    switch (s.K) {
+        case 64: return run_recurrent_k<TI, 64>(s, gate, io, st);
+        case 128: return run_recurrent_k<TI, 128>(s, gate, io, st);
+        case 160: return run_recurrent_k<TI, 160>(s, gate, io, st);
+        case 192: return run_recurrent_k<TI, 192>(s, gate, io, st);
+        case 256: return run_recurrent_k<TI, 256>(s, gate, io, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
 }  // namespace
+
+bool recurrent_key_width(int K) { return K == 64 || K == 128 || K == 160 || K == 192 || K == 256; }
 
 cudaError_t launch_recurrent(const Shape& s, int bf16, int gate, int T, const int32_t* cu, const void* q,
                              const void* k, const void* v, const void* beta, const float* g, const float* h0,
                              void* o, float* ht, int32_t* err, const float* A_log, const float* dt_bias,
                              float lower_bound, int qk_norm, float eps, cudaStream_t st, const Gdn2& gd, int group) {
-    if (s.V % RV != 0 || (s.K != 64 && s.K != 128)) return cudaErrorInvalidValue;
+    if (s.V % RV != 0 || !recurrent_key_width(s.K)) return cudaErrorInvalidValue;
     RecIO io{q, k, v, beta, g, h0, cu, o, ht, err, T, A_log, dt_bias, lower_bound, eps, qk_norm, gd.erase, gd.write,
              group};
-    if (bf16) return s.K == 128 ? run_recurrent_k<__nv_bfloat16, 128>(s, gate, io, st)
-                                : run_recurrent_k<__nv_bfloat16, 64>(s, gate, io, st);
-    return s.K == 128 ? run_recurrent_k<float, 128>(s, gate, io, st) : run_recurrent_k<float, 64>(s, gate, io, st);
+    return bf16 ? run_recurrent_t<__nv_bfloat16>(s, gate, io, st) : run_recurrent_t<float>(s, gate, io, st);
 }
 
 }  // namespace kda

@@ -63,13 +63,14 @@ typedef enum { KDA_GATE_NONE = 0, KDA_GATE_SCALAR = 1, KDA_GATE_CHANNEL = 2 } kd
 
 typedef struct {
     int B, T, H, K, V;          /* batch, tokens per sequence (total tokens when packed),
-                                   heads, key width (1..128), value width (1..4096). Other
+                                   heads, key width (1..128; the token-by-token call also
+                                   160, 192, 256), value width (1..4096). Other
                                    than K = V = 64 or 128 the chunked calls run zero-padded;
                                    V above 128 runs as ceil(V / 128) value blocks, each a
                                    value head of its own (the delta-rule update moves every
                                    value column of the state independently, "ReWY" paper,
                                    the state recurrence). The token-by-token call needs
-                                   K = 64 or 128 and V a multiple of 32 (up to 4096). */
+                                   K = 64, 128, 160, 192 or 256 and V a multiple of 32. */
     int N;                      /* packed sequences (used only when cu_seqlens != NULL) */
     const int32_t *cu_seqlens;  /* device, N+1 non-decreasing token offsets, first 0,
                                    last B*T; NULL for equal-length sequences */

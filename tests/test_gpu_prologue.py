@@ -116,7 +116,7 @@ def test_prologue_policies_agree_and_are_deterministic():
 
 
 @pytest.mark.parametrize("io,gate,K,lb", [("fp32", "channel", 64, 0.0), ("bf16", "channel", 128, -5.0),
-                                          ("bf16", "scalar", 128, 0.0)])
+                                          ("bf16", "scalar", 128, 0.0), ("fp32", "channel", 192, 0.0)])
 def test_recurrent_prologue_matches_oracle(io, gate, K, lb):
     import chunkwise_delta_rule_gb300 as kda
     case, A, dt, lb = prologue_case(io, gate, 2, 40, 2, K, 73, lb)

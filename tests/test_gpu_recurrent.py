@@ -48,6 +48,10 @@ CASES = [
     dict(io="bf16", gate="scalar", B=2, T=9, H=2, K=128, V=256),
     dict(io="fp32", gate="channel", B=1, T=20, H=3, K=64, V=96),
     dict(io="bf16", gate="channel", B=2, T=3, H=2, K=128, V=32),
+    # key widths above 128 (the token-by-token kernel only): 192/160, 256, 160
+    dict(io="bf16", gate="channel", B=2, T=12, H=2, K=192, V=160),
+    dict(io="fp32", gate="scalar", B=1, T=9, H=2, K=256, V=256),
+    dict(io="fp32", gate="channel", B=2, T=5, H=1, K=160, V=64),
 ]
 
 
