@@ -314,7 +314,7 @@ def run_ours(args):
     save = 1 if args.policy == "save" else 0
     p = kda.make_problem(case.q, case.k, case.v, case.g, None if args.gdn2 else case.beta, gate=case.gate,
                          scale=case.scale, initial_state=case.h0, cu_seqlens=case.cu_seqlens,
-                         save_policy=save, qk_l2norm=bool(args.prologue), **pro)
+                         save_policy=save, qk_l2norm=bool(args.prologue), schedule=args.schedule, **pro)
     wf = torch.empty(kda.kda_workspace_size(p, False), dtype=torch.uint8, device=dev)
     wb = torch.empty(kda.kda_workspace_size(p, True), dtype=torch.uint8, device=dev)
     sv = torch.empty(kda.kda_saved_size(p), dtype=torch.uint8, device=dev) if save else None
@@ -375,8 +375,19 @@ def run_ours(args):
     tflops_exec = ws * (fl_f + fl_b + (fl_r if args.policy == "recompute" else 0.0)) / (step_ms * 1e-3) / 1e12
     pk = peaks()
     launches = sum(v[0] for v in kern.values())
-    # dominant kernel and its roofline
+    # dominant kernel and its roofline. With a backward in P time pieces the reverse scan and the
+    # consumer run P launches per step, each over 1/P of the units: their per-launch work and
+    # traffic are a pass's divided by P.
+    pieces = max(1, round(kern.get("k_bwd_consumer_tc", (K, 0.0))[0] / K))
     work = kernel_work(case, save=bool(save))
+    for kname in ("k_bwd_scan_tc", "k_bwd_consumer_tc"):
+        if kname in work:
+            work[kname] = (work[kname][0] / pieces, work[kname][1] / pieces)
+
+    def traffic_per_launch(kname):
+        tr = traffic_for(kname)
+        return None if tr is None else (tr / pieces if kname in ("k_bwd_scan_tc", "k_bwd_consumer_tc") else tr)
+
     dom = max(kern.items(), key=lambda kv: kv[1][1])[0] if kern else None
     roof = None
     if dom:
@@ -396,7 +407,8 @@ def run_ours(args):
                 achieved = fl / (avg_ms * 1e-3) / 1e12
                 roof = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 2), "peak": pk["bf16"],
                         "unit": "TFLOP/s", "frac": round(achieved / pk["bf16"], 4)}
-            roof.update({"traffic": traffic_for(dom), "avg_launch_ms": round(avg_ms, 4),
+            roof.update({"traffic": traffic_per_launch(dom), "avg_launch_ms": round(avg_ms, 4),
+                         "launches_per_step": round(n_l / K, 2),
                          "algorithmic_bytes": by, "algorithmic_flops": fl,
                          "tensor_frac_of_bf16_peak": round(fl / (avg_ms * 1e-3) / 1e12 / pk["bf16"], 4),
                          "peak_source": pk["source"] + " (MEASURED_PEAKS.json)", "sm_mhz_under_load": sm_mhz})
@@ -435,6 +447,7 @@ def run_ours(args):
             "config": {"workload": cfg["name"] + (f"_first{case.H}heads" if args.heads else ""), "B": case.B, "T": case.T, "H": case.H, "dk": case.K,
                        "dv": case.V, "gate": case.gate, "io": cfg["io"], "chunk": BT,
                        "policy": args.policy, "parallelism": f"replicas x{ws}",
+                       "backward_pieces": pieces,
                        "prologue": ("raw gate activated in the operator (softplus form, A_log, dt_bias) and "
                                     "q/k L2-normalised in the operator") if args.prologue else "off",
                        "key_heads": case.q.shape[2],
@@ -712,6 +725,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=WORKLOAD_IDX)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--schedule", type=int, default=0,
+                    help="backward schedule: 0 the library's choice, 1 one pass, P >= 2 time pieces")
     ap.add_argument("--clocks-csv", default="",
                     help="keep the raw nvidia-smi clock samples of the timed region in this file")
     ap.add_argument("--no-cpu", action="store_true")

@@ -21,6 +21,7 @@ size_t up(size_t x) { return (x + ALIGN - 1) / ALIGN * ALIGN; }
 
 struct Dims {
     int N = 0, NC = 0, Ttot = 0, D = 0, H = 0;
+    int per = 0;   // chunks per sequence of an equal-length batch (0: packed sequences)
 };
 
 // Checks the size fields; fills d. Returns KDA_OK or an error (message set). The chunked calls
@@ -38,6 +39,8 @@ kda_status check_dims(const kda_problem* p, Dims& d, bool chunked = true) {
         return fail(KDA_ERR_INVALID_ARG, "unknown gate kind");
     if (p->save_policy != 0 && p->save_policy != 1)
         return fail(KDA_ERR_INVALID_ARG, "save_policy must be 0 or 1");
+    if (p->schedule < 0 || p->schedule > kda::MAX_PIECES)
+        return fail(KDA_ERR_INVALID_ARG, "schedule must be 0 (default), 1 (one pass) or a piece count up to 8");
     if (p->qk_l2norm != 0 && p->qk_l2norm != 1) return fail(KDA_ERR_INVALID_ARG, "qk_l2norm must be 0 or 1");
     if (p->HV != 0 && p->HV != p->H && (p->HV < p->H || p->HV % p->H != 0 || p->HV > 65535))
         return fail(KDA_ERR_INVALID_ARG, "HV must be 0 or a multiple of H (at most 65535)");
@@ -65,6 +68,7 @@ kda_status check_dims(const kda_problem* p, Dims& d, bool chunked = true) {
     } else {
         d.N = p->B;
         d.NC = (int)(per * p->B);
+        d.per = (int)per;
     }
     return KDA_OK;
 }
@@ -72,6 +76,7 @@ kda_status check_dims(const kda_problem* p, Dims& d, bool chunked = true) {
 struct Layout {
     size_t table = 0, fcore = 0, fextra = 0, bwd = 0;   // CUDA-core path
     size_t ftc = 0, ftc_b = 0, btc = 0, wscr = 0;       // tensor-core path
+    size_t piece = 0;   // time pieces of the tensor-core backward: two state adjoints, the claim counters
 };
 
 // The tensor-core path serves bf16 I/O at K = V = 128; everything else runs
@@ -94,6 +99,7 @@ Layout layout(const Dims& d) {
     L.ftc_b = up(2 * chd * BT * BT) + up(2 * chd * D * D) + up(2 * chd * BT * D);
     L.btc = up(2 * chd * D * D) + up(2 * chd * BT * D);
     L.wscr = up(4 * chd * BT * D) * 3 + up(4 * chd * BT * BT) * 2 + up(4 * chd * D) + up(4 * chd * BT);
+    if (d.per) L.piece = 2 * up(4 * N * H * D * D) + up(4 * kda::MAX_PIECES);
     return L;
 }
 
@@ -483,6 +489,19 @@ cudaError_t side_join(Side* sd, cudaStream_t main) {
 // one CTA per SM) are resident together.
 bool scans_fit_together(const kda::Shape& s) { return 2L * s.N * s.H <= (long)kda::sm_count(); }
 
+// Time pieces of the tensor-core backward (equal-length batches only): the reverse scan runs piece by
+// piece, latest first, and each piece's units are consumed on the side stream while the scan goes on
+// with the next piece, on the SMs it leaves idle. schedule 1 = one pass, P >= 2 = P pieces, 0 = the
+// library's choice (DEFAULT_PIECES when the scan's CTAs fill at most half of the SMs). At least two
+// chunks per piece.
+int bwd_pieces(const kda_problem* p, const Dims& d) {
+    if (!d.per) return 1;
+    int P = p->schedule >= 2 ? p->schedule : p->schedule == 1 ? 1
+            : (2L * d.N * d.H <= (long)kda::sm_count() ? kda::DEFAULT_PIECES : 1);
+    while (P > 1 && d.per < 2 * P) --P;
+    return P;
+}
+
 }  // namespace
 
 namespace kda {
@@ -499,7 +518,7 @@ static size_t core_workspace(const kda_problem* p, const Dims& d, int for_backwa
     const Layout L = layout(d);
     if (use_tc(p)) {
         if (!for_backward) return L.table + (p->save_policy ? 0 : L.ftc);
-        return L.table + (p->save_policy ? 0 : L.ftc + L.ftc_b) + L.btc + L.wscr;
+        return L.table + (p->save_policy ? 0 : L.ftc + L.ftc_b) + L.btc + L.wscr + L.piece;
     }
     if (!for_backward) return L.table + (p->save_policy ? 0 : L.fcore);
     return L.table + (p->save_policy ? 0 : L.fcore + L.fextra) + L.bwd;
@@ -678,11 +697,41 @@ static kda_status chunk_bwd_core(const kda_problem* p, const void* dout, const f
             e = traced("k_fwd_scan_tc_recompute", rs, [&] { return kda::launch_fwd_scan_tc(s, 2, p->h0, t, f, nullptr, nullptr, rs); });
             if (e != cudaSuccess) return cuda_fail(e, "forward scan (recompute)");
         }
-        e = traced("k_bwd_scan_tc", cs, [&] { return kda::launch_bwd_scan_tc(s, dout, dht, t, f, b, dh0, cs); });
-        if (e != cudaSuccess) return cuda_fail(e, "reverse scan");
-        if (sd && (e = side_join(sd, cs)) != cudaSuccess) return cuda_fail(e, "side stream");
-        e = traced("k_bwd_consumer_tc", cs, [&] { return kda::launch_bwd_consumer_tc(s, gate, p->q, p->k, p->v, p->beta, p->g, dout, t, f, b, dq, dk, dv, dbeta, dg, cs, gd); });
-        if (e != cudaSuccess) return cuda_fail(e, "consumer");
+        int P = bwd_pieces(p, d);
+        if (P > 1 && !sd) {
+            sd = side_stream();
+            if (!sd) P = 1;
+            else if ((e = side_fork(sd, cs)) != cudaSuccess) return cuda_fail(e, "side stream");
+        }
+        if (P <= 1) {
+            e = traced("k_bwd_scan_tc", cs, [&] { return kda::launch_bwd_scan_tc(s, dout, dht, t, f, b, dh0, cs); });
+            if (e != cudaSuccess) return cuda_fail(e, "reverse scan");
+            if (sd && (e = side_join(sd, cs)) != cudaSuccess) return cuda_fail(e, "side stream");
+            e = traced("k_bwd_consumer_tc", cs, [&] { return kda::launch_bwd_consumer_tc(s, gate, p->q, p->k, p->v, p->beta, p->g, dout, t, f, b, dq, dk, dv, dbeta, dg, cs, gd); });
+            if (e != cudaSuccess) return cuda_fail(e, "consumer");
+        } else {
+            // time pieces: the scan of piece q+1 (main stream) runs beside the consumer of piece q (side
+            // stream, which also holds the recompute scan under policy R); the state adjoint entering a
+            // piece goes to the next through one of two fp32 buffers
+            float* hb[2] = {cw.take<float>(state_bytes(d)), cw.take<float>(state_bytes(d))};
+            int* ctr = cw.take<int>(4 * kda::MAX_PIECES);
+            if ((e = cudaMemsetAsync(ctr, 0, 4 * kda::MAX_PIECES, cs)) != cudaSuccess) return cuda_fail(e, "claim counters");
+            for (int q = 0; q < P; ++q) {
+                kda::ConsPiece pc;
+                pc.per = d.per;
+                pc.lo = (int)((long)d.per * (P - 1 - q) / P);
+                pc.L = (int)((long)d.per * (P - q) / P) - pc.lo;
+                pc.ctr = ctr + q;
+                const float* din = q == 0 ? dht : hb[(q - 1) & 1];
+                float* dnext = q == P - 1 ? dh0 : hb[q & 1];
+                e = traced("k_bwd_scan_tc", cs, [&] { return kda::launch_bwd_scan_tc(s, dout, din, t, f, b, dnext, cs, pc); });
+                if (e != cudaSuccess) return cuda_fail(e, "reverse scan");
+                if ((e = side_fork(sd, cs)) != cudaSuccess) return cuda_fail(e, "side stream");
+                e = traced("k_bwd_consumer_tc", sd->st, [&] { return kda::launch_bwd_consumer_tc(s, gate, p->q, p->k, p->v, p->beta, p->g, dout, t, f, b, dq, dk, dv, dbeta, dg, sd->st, gd, pc); });
+                if (e != cudaSuccess) return cuda_fail(e, "consumer");
+            }
+            if ((e = side_join(sd, cs)) != cudaSuccess) return cuda_fail(e, "side stream");
+        }
         if (gate != KDA_GATE_NONE) {
             e = traced("k_bwd_wide", cs, [&] { return kda::launch_bwd_wide(s, gate, p->q, p->k, p->v, p->beta, p->g, dout, t, f, b, scr, dq, dk, dv, dbeta, dg, cs, gd); });
             if (e != cudaSuccess) return cuda_fail(e, "consumer (wide chunks)");

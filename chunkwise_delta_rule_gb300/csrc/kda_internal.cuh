@@ -264,12 +264,22 @@ cudaError_t launch_prep_wide(const Shape& s, int gate, const void* q, const void
 cudaError_t launch_fwd_scan_tc(const Shape& s, int mode, const float* h0, Table t, FwdTC f, void* o,
                                float* ht, cudaStream_t st);
 
+// A time piece of the backward for a batch of equal-length sequences of `per` chunks each: chunks
+// lo .. lo+L-1 of every sequence (L = 0: every chunk of every sequence). The reverse scan runs one
+// piece per launch, latest first, handing the state adjoint on through dht / dh0; the consumer of a
+// piece claims its units from ctr (zeroed before the launch; NULL: a fixed stride per CTA).
+constexpr int MAX_PIECES = 8;       // time pieces of the tensor-core backward, at most
+constexpr int DEFAULT_PIECES = 3;   // the library's choice when the reverse scan leaves SMs idle (measured)
+struct ConsPiece {
+    int lo = 0, L = 0, per = 0;
+    int* ctr = nullptr;
+};
 cudaError_t launch_bwd_scan_tc(const Shape& s, const void* dout, const float* dht, Table t, FwdTC f,
-                               BwdTC b, float* dh0, cudaStream_t st);
+                               BwdTC b, float* dh0, cudaStream_t st, const ConsPiece& pc = ConsPiece{});
 cudaError_t launch_bwd_consumer_tc(const Shape& s, int gate, const void* q, const void* k, const void* v,
                                    const void* beta, const float* g, const void* dout, Table t, FwdTC f,
                                    BwdTC b, void* dq, void* dk, void* dv, void* dbeta, float* dg,
-                                   cudaStream_t st, const Gdn2& gd = Gdn2{});
+                                   cudaStream_t st, const Gdn2& gd = Gdn2{}, const ConsPiece& pc = ConsPiece{});
 // CUDA-core consumers for the WIDE chunks of the tensor-core path (reading its
 // bf16 intermediates, fp32 scratch in `scratch`).
 cudaError_t launch_bwd_wide(const Shape& s, int gate, const void* q, const void* k, const void* v,

@@ -319,7 +319,7 @@ __device__ __forceinline__ void bscan_issue(const Shape& s, const Table& t, cons
 
 __global__ void __launch_bounds__(ST_ALL, 1)
     k_bwd_scan_tc(Shape s, const __grid_constant__ CUtensorMap tmo, const float* __restrict__ dht, Table t,
-                  FwdTC f, BwdTC b, float* __restrict__ dh0) {
+                  FwdTC f, BwdTC b, float* __restrict__ dh0, int plo, int pl) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                            ~static_cast<uintptr_t>(1023));
@@ -328,7 +328,9 @@ __global__ void __launch_bounds__(ST_ALL, 1)
     uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 6);
     const uint32_t sb = tc::smem_u32(base);
     const int nseq = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5;
-    const int c0 = t.seq_chunk0[nseq], c1 = t.seq_chunk0[nseq + 1];
+    // the sequence's chunks, or those of one time piece (chunks plo .. plo+pl-1 of it): dht is then
+    // the state adjoint leaving the piece and dh0 the one entering it
+    const int c0 = t.seq_chunk0[nseq] + (pl ? plo : 0), c1 = pl ? c0 + pl : t.seq_chunk0[nseq + 1];
     const bool issuer = warp == ST / 32;
     int filled = 0, waited = 0;   // bulk fills issued / consumed (issuer lane 0)
 
@@ -415,12 +417,29 @@ __device__ __forceinline__ float ldsw(const unsigned char* tile, int r, int col)
     return __bfloat162float(*reinterpret_cast<const bf16*>(tile + tc::sw128_off(BT, r, col * 2)));
 }
 
-// The next unit of this CTA after u that has tokens and a narrow gate range
-// (-1 when none is left); its chunk extent through n and tok0.
+// Units of one consumer launch, as an index space i in [0, units): all units (L == 0, i = u), or, for
+// a batch of equal-length sequences of `per` chunks each, chunks lo .. lo+L-1 of every sequence
+// (i runs over sequence, then chunk, then head). A CTA takes index blockIdx.x first; later indices
+// come from the launch's counter (zeroed before the launch) or, without one, in strides of gridDim.
+__device__ __forceinline__ int piece_units(const ConsPiece& pc, int N, int H, int total) {
+    return pc.L ? N * pc.L * H : total;
+}
+__device__ __forceinline__ int piece_unit(const ConsPiece& pc, int i, int H) {
+    if (!pc.L) return i;
+    const int LH = pc.L * H, n = i / LH, r = i - n * LH;
+    return (n * pc.per + pc.lo + r / H) * H + r % H;
+}
+__device__ __forceinline__ int claim_next(const ConsPiece& pc, int i) {
+    return pc.ctr ? (int)gridDim.x + atomicAdd(pc.ctr, 1) : i + (int)gridDim.x;
+}
+
+// The first unit at index i or after it (claiming further indices) that has tokens and a narrow
+// gate range (-1 when none is left); i ends at that unit's index, n and tok0 give its chunk extent.
 template <int GATE>
-__device__ __forceinline__ int cons_next(int u, int total, int H, const Table& t, const FwdTC& f, int& n, int& tok0) {
-    for (u += gridDim.x; u < total; u += gridDim.x) {
-        const int c = u / H;
+__device__ __forceinline__ int cons_find(int& i, int units, const ConsPiece& pc, int H, const Table& t,
+                                         const FwdTC& f, int& n, int& tok0) {
+    for (; i < units; i = claim_next(pc, i)) {
+        const int u = piece_unit(pc, i, H), c = u / H;
         n = t.chunk_len[c];
         if (n > 0 && (GATE == 0 || f.WIDE[u] == 0)) {
             tok0 = t.chunk_tok0[c];
@@ -491,7 +510,7 @@ __global__ void __launch_bounds__(CT, 1)
                       const bf16* __restrict__ beta,
                       const float* __restrict__ g, Table t, FwdTC f, BwdTC bw, bf16* __restrict__ dq,
                       bf16* __restrict__ dk, bf16* __restrict__ dv, bf16* __restrict__ dbeta,
-                      float* __restrict__ dg, Gdn2 gd) {
+                      float* __restrict__ dg, Gdn2 gd, ConsPiece pc) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                            ~static_cast<uintptr_t>(1023));
@@ -520,8 +539,9 @@ __global__ void __launch_bounds__(CT, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = warp & 3, grp = warp >> 2;
-    const int H = s.H, total = s.NC * s.H;
+    const int H = s.H, units = piece_units(pc, s.N, s.H, s.NC * s.H);
     const float scale = s.scale;
+    int icur = (int)blockIdx.x, icand = units;   // indices of the current unit and the candidate (thread LDR)
     int nC = 0, nX1 = 0, nX2 = 0;   // load groups issued (thread LDR)
     int wC = 0, wX1 = 0, wX2 = 0;   // load groups waited for (every thread)
 
@@ -529,7 +549,7 @@ __global__ void __launch_bounds__(CT, 1)
         for (int i = 0; i < 4; ++i) tc::mbar_init(&bar[i], 1);
         tc::fence_mbar_init();
         int n0 = 0, t0 = 0;
-        const int u0 = cons_next<GATE>((int)blockIdx.x - (int)gridDim.x, total, H, t, f, n0, t0);
+        const int u0 = cons_find<GATE>(icur, units, pc, H, t, f, n0, t0);
         sMeta[0] = u0;
         sMeta[1] = n0;
         sMeta[2] = t0;
@@ -559,9 +579,10 @@ __global__ void __launch_bounds__(CT, 1)
         const int n = meta[1], tok0 = meta[2];
         const int c = u / H, h = u - c * H;
         const size_t ch = (size_t)u;
-        if (tid == LDR) {   // table entries of the next candidate, used after the phase-B MMAs
-            cand = u + (int)gridDim.x;
-            if (cand < total) {
+        if (tid == LDR) {   // the next candidate and its table entries, used after the phase-B MMAs
+            icand = claim_next(pc, icur);
+            if (icand < units) {
+                cand = piece_unit(pc, icand, H);
                 cn = __ldg(t.chunk_len + cand / H);
                 ct0 = __ldg(t.chunk_tok0 + cand / H);
                 cw = (GATE != 0) ? __ldg(f.WIDE + cand) : 0;
@@ -782,12 +803,14 @@ __global__ void __launch_bounds__(CT, 1)
         int nxt = -1;
         if (tid == LDR) {
             int nn = 0, nt = 0;
-            if (cand < total && cn > 0 && cw == 0) {
+            if (icand < units && cn > 0 && cw == 0) {
                 nxt = cand;
                 nn = cn;
                 nt = ct0;
-            } else if (cand < total) {
-                nxt = cons_next<GATE>(cand, total, H, t, f, nn, nt);
+                icur = icand;
+            } else if (icand < units) {
+                icur = claim_next(pc, icand);
+                nxt = cons_find<GATE>(icur, units, pc, H, t, f, nn, nt);
             }
             int* nm = sMeta + 4 * ((k + 1) & 1);
             nm[0] = nxt;
@@ -1043,7 +1066,7 @@ __global__ void __launch_bounds__(CT, 1)
 template <int GATE, bool GD2>
 cudaError_t run_consumer(const Shape& s, const void* q, const void* k, const void* v, const void* beta,
                          const float* g, const void* dout, Table t, FwdTC f, BwdTC b, void* dq, void* dk,
-                         void* dv, void* dbeta, float* dg, cudaStream_t st, const Gdn2& gd) {
+                         void* dv, void* dbeta, float* dg, cudaStream_t st, const Gdn2& gd, const ConsPiece& pc) {
     cudaError_t e = set_smem_once<k_bwd_consumer_tc<GATE, GD2>>(CONS_SMEM);
     if (e != cudaSuccess) return e;
     CUtensorMap mq, mk, mo, mg, mv, mdg;
@@ -1053,38 +1076,39 @@ cudaError_t run_consumer(const Shape& s, const void* q, const void* k, const voi
         !tmap_rows_bf16(&mo, dout, s.Ttot, s.H, D) || !tmap_rows_bf16(&mv, v, s.Ttot, s.H, D) ||
         (GATE == 2 && (!tmap_rows_f32(&mg, g, s.Ttot, s.H, D) || !tmap_rows_f32(&mdg, dg, s.Ttot, s.H, D))))
         return cudaErrorInvalidValue;
-    const long units = (long)s.NC * s.H;
+    const long units = pc.L ? (long)s.N * pc.L * s.H : (long)s.NC * s.H;
     if (units <= 0) return cudaSuccess;
+    if (units > 0x7fffffffL) return cudaErrorInvalidValue;
     const int grid = (int)(units < sm_count() ? units : sm_count());   // one CTA per SM, persistent
     k_bwd_consumer_tc<GATE, GD2><<<grid, CT, CONS_SMEM, st>>>(s, mq, mk, mo, mg, mv, mdg, (const bf16*)beta, g, t, f, b,
-                                                         (bf16*)dq, (bf16*)dk, (bf16*)dv, (bf16*)dbeta, dg, gd);
+                                                         (bf16*)dq, (bf16*)dk, (bf16*)dv, (bf16*)dbeta, dg, gd, pc);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_bwd_scan_tc(const Shape& s, const void* dout, const float* dht, Table t, FwdTC f, BwdTC b,
-                               float* dh0, cudaStream_t st) {
+                               float* dh0, cudaStream_t st, const ConsPiece& pc) {
     cudaError_t e = set_smem_once<k_bwd_scan_tc>(BSCAN_SMEM);
     if (e != cudaSuccess) return e;
     CUtensorMap mo;
     if (!tmap_rows_bf16(&mo, dout, s.Ttot, s.H, D)) return cudaErrorInvalidValue;
     dim3 grid(s.N, s.H);
-    k_bwd_scan_tc<<<grid, ST_ALL, BSCAN_SMEM, st>>>(s, mo, dht, t, f, b, dh0);
+    k_bwd_scan_tc<<<grid, ST_ALL, BSCAN_SMEM, st>>>(s, mo, dht, t, f, b, dh0, pc.lo, pc.L);
     return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_consumer_tc(const Shape& s, int gate, const void* q, const void* k, const void* v,
                                    const void* beta, const float* g, const void* dout, Table t, FwdTC f,
                                    BwdTC b, void* dq, void* dk, void* dv, void* dbeta, float* dg,
-                                   cudaStream_t st, const Gdn2& gd) {
+                                   cudaStream_t st, const Gdn2& gd, const ConsPiece& pc) {
     switch (gate) {
-        case 0: return gd.erase ? run_consumer<0, true>(s, q, k, v, beta, g, dout, t, f, b, dq, dk, dv, dbeta, dg, st, gd)
-                                : run_consumer<0, false>(s, q, k, v, beta, g, dout, t, f, b, dq, dk, dv, dbeta, dg, st, gd);
-        case 1: return gd.erase ? run_consumer<1, true>(s, q, k, v, beta, g, dout, t, f, b, dq, dk, dv, dbeta, dg, st, gd)
-                                : run_consumer<1, false>(s, q, k, v, beta, g, dout, t, f, b, dq, dk, dv, dbeta, dg, st, gd);
-        default: return gd.erase ? run_consumer<2, true>(s, q, k, v, beta, g, dout, t, f, b, dq, dk, dv, dbeta, dg, st, gd)
-                                 : run_consumer<2, false>(s, q, k, v, beta, g, dout, t, f, b, dq, dk, dv, dbeta, dg, st, gd);
+        case 0: return gd.erase ? run_consumer<0, true>(s, q, k, v, beta, g, dout, t, f, b, dq, dk, dv, dbeta, dg, st, gd, pc)
+                                : run_consumer<0, false>(s, q, k, v, beta, g, dout, t, f, b, dq, dk, dv, dbeta, dg, st, gd, pc);
+        case 1: return gd.erase ? run_consumer<1, true>(s, q, k, v, beta, g, dout, t, f, b, dq, dk, dv, dbeta, dg, st, gd, pc)
+                                : run_consumer<1, false>(s, q, k, v, beta, g, dout, t, f, b, dq, dk, dv, dbeta, dg, st, gd, pc);
+        default: return gd.erase ? run_consumer<2, true>(s, q, k, v, beta, g, dout, t, f, b, dq, dk, dv, dbeta, dg, st, gd, pc)
+                                 : run_consumer<2, false>(s, q, k, v, beta, g, dout, t, f, b, dq, dk, dv, dbeta, dg, st, gd, pc);
     }
 }
 

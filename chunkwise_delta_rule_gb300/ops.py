@@ -61,13 +61,16 @@ def make_problem(q, k, v, g, beta, *, gate: str, scale: Optional[float] = None,
                  cu_seqlens: Optional[torch.Tensor] = None, save_policy: int = 0,
                  A_log: Optional[torch.Tensor] = None, dt_bias: Optional[torch.Tensor] = None,
                  lower_bound: float = 0.0, qk_l2norm: bool = False, l2norm_eps: float = 1e-6,
-                 erase: Optional[torch.Tensor] = None, write: Optional[torch.Tensor] = None) -> Problem:
+                 erase: Optional[torch.Tensor] = None, write: Optional[torch.Tensor] = None,
+                 schedule: int = 0) -> Problem:
     """Describe one call. With ``A_log`` (fp32 [H]) ``g`` is the raw gate and the
     decay is activated inside the operator (softplus form, or the lower-bound
     form when ``lower_bound`` < 0), with the optional ``dt_bias`` (fp32, [H, K]
     for a per-channel gate, [H] for a scalar one); ``qk_l2norm`` normalises q
     and k per (token, head) first. GatedDeltaNet-2: ``erase`` [B, T, H, K] and
     ``write`` [B, T, H, V] (the I/O dtype) replace ``beta``, which may be None.
+    ``schedule``: 0 the library's choice, 1 one reverse-scan pass before the
+    consumer, P >= 2 that many time pieces (equal-length batches; see kda.h).
     Grouped value heads: v may carry HV = G * H heads (q, k keep H); then every
     per-head tensor but q and k has HV heads (read H as HV above)."""
     _need(q.dim() == 4 and k.shape == q.shape, "q and k must be [B, T, H, K]")
@@ -119,7 +122,7 @@ def make_problem(q, k, v, g, beta, *, gate: str, scale: Optional[float] = None,
     c.g = None if g is None else g.data_ptr()
     c.h0 = None if initial_state is None else initial_state.data_ptr()
     c.save_policy = int(save_policy)
-    c.schedule = 0
+    c.schedule = int(schedule)
     if A_log is not None:
         _need(gate != "none", "A_log needs a gate")
         _need(A_log.dtype == torch.float32 and A_log.is_cuda and A_log.is_contiguous()

@@ -88,7 +88,12 @@ typedef struct {
     const float *h0;            /* [N, H, K, V] fp32 or NULL (zero initial state) */
     int save_policy;            /* 0: backward recomputes the forward (policy R);
                                    1: forward fills `saved` for the backward (policy A) */
-    int schedule;               /* 0: default; reserved for producer/consumer schedules */
+    int schedule;               /* backward schedule of the tensor-core path for equal-length
+                                   batches: 0 = the library's choice; 1 = one reverse-scan pass,
+                                   then the consumer; P = 2..8 = P time pieces, the reverse scan
+                                   of piece q+1 running beside the consumer of piece q (on a
+                                   library-owned second stream). Results are identical bitwise
+                                   for every value; other paths ignore it. */
     /* Optional prologue inside the operator ("GatedDeltaNet-2 (NVlabs) — official spec
      * transcription", §2.0, §3, §4.2); all zero / NULL turns it off. */
     const float *A_log;         /* [H] fp32 or NULL. Non-NULL (needs a gate): g holds the raw gate and

@@ -40,7 +40,7 @@ def _prob(**kw):
     p.g = fake if p.gate != 0 else None
     p.h0 = None
     p.save_policy = kw.get("save", 0)
-    p.schedule = 0
+    p.schedule = kw.get("schedule", 0)
     return p
 
 
@@ -71,10 +71,12 @@ def test_workspace_size_arithmetic():
     ftc_b = up(2 * chd * BT * BT) + up(2 * chd * D * D) + up(2 * chd * BT * D)
     btc = up(2 * chd * D * D) + up(2 * chd * BT * D)
     wscr = up(4 * chd * BT * D) * 3 + up(4 * chd * BT * BT) * 2 + up(4 * chd * D) + up(4 * chd * BT)
-    assert _ws(ptc, 1) == table + ftc + ftc_b + btc + wscr
+    # equal-length batches: two fp32 state adjoints and eight claim counters for a backward in time pieces
+    piece = 2 * up(4 * 2 * H * D * D) + up(4 * 8)
+    assert _ws(ptc, 1) == table + ftc + ftc_b + btc + wscr + piece
     ptca = _prob(io=0, save=1)
     assert _ws(ptca, 0) == table
-    assert _ws(ptca, 1) == table + btc + wscr
+    assert _ws(ptca, 1) == table + btc + wscr + piece
     assert _lib.load().kda_saved_size(ctypes.byref(ptca)) == ftc + ftc_b
     pa = _prob(save=1, io=1)
     assert _ws(pa, 0) == table
@@ -97,6 +99,8 @@ def test_workspace_size_arithmetic():
     (dict(io=5), 1),
     (dict(B=2, cu=0x2000, N=3), 1),
     (dict(save=3), 1),
+    (dict(schedule=9), 1),
+    (dict(schedule=-1), 1),
 ])
 def test_invalid_problems_are_rejected_before_launch(kw, status):
     lib = _lib.load()
