@@ -492,12 +492,13 @@ bool scans_fit_together(const kda::Shape& s) { return 2L * s.N * s.H <= (long)kd
 // Time pieces of the tensor-core backward (equal-length batches only): the reverse scan runs piece by
 // piece, latest first, and each piece's units are consumed on the side stream while the scan goes on
 // with the next piece, on the SMs it leaves idle. schedule 1 = one pass, P >= 2 = P pieces, 0 = the
-// library's choice (DEFAULT_PIECES when the scan's CTAs fill at most half of the SMs). At least two
-// chunks per piece.
+// library's choice: DEFAULT_PIECES when the intermediates are saved and the scan's CTAs fill at most
+// half of the SMs (under recompute the side stream already carries the recomputed scan ahead of the
+// consumers, and one pass measured faster). At least two chunks per piece.
 int bwd_pieces(const kda_problem* p, const Dims& d) {
     if (!d.per) return 1;
     int P = p->schedule >= 2 ? p->schedule : p->schedule == 1 ? 1
-            : (2L * d.N * d.H <= (long)kda::sm_count() ? kda::DEFAULT_PIECES : 1);
+            : (p->save_policy && 2L * d.N * d.H <= (long)kda::sm_count() ? kda::DEFAULT_PIECES : 1);
     while (P > 1 && d.per < 2 * P) --P;
     return P;
 }
