@@ -2,6 +2,9 @@
 
 from __future__ import annotations
 
+import json
+import os
+
 import numpy as np
 
 
@@ -33,3 +36,16 @@ def check_close(name, x, ref, tol, abs_floor=1e-6):
     err = rel_err(x, ref)
     assert err <= tol, f"{name}: normwise relative error {err:.3e} > {tol}"
     return err
+
+
+def record_errors(case_name, errs, **extra):
+    """Appends one JSON line {case, errors per tensor, ...} to the file named by the environment
+    variable KDA_PARITY_REPORT (nothing when it is unset): the per-tensor error margins of a GPU
+    parity run, kept for the record."""
+    path = os.environ.get("KDA_PARITY_REPORT")
+    if not path:
+        return
+    rec = {"case": case_name, "errors": {k: float(v) for k, v in errs.items()}}
+    rec.update(extra)
+    with open(path, "a") as fh:
+        fh.write(json.dumps(rec) + "\n")

@@ -9,7 +9,7 @@ import numpy as np
 import pytest
 import torch
 
-from tests.helpers import check_close, np64, run_oracle, run_oracle_pairs
+from tests.helpers import check_close, np64, record_errors, run_oracle, run_oracle_pairs
 from workloads import CONFIGS, make_case, make_config_case
 
 pytestmark = pytest.mark.gpu
@@ -133,6 +133,20 @@ def test_zero_and_tiny_beta(mode):
     compare_full(case, got, run_oracle(case), TOL["fp32"])
 
 
+@pytest.mark.parametrize("policy", [0, 1], ids=["recompute", "save"])
+@pytest.mark.parametrize("gate", ["channel", "scalar"])
+@pytest.mark.parametrize("mode", ["zero_every3", "tiny"])
+def test_zero_and_tiny_beta_tensor_core(mode, gate, policy):
+    """beta = 0 on every third token, or 1e-8 everywhere, on the tensor-core path (bf16, K = V = 128)
+    under both policies; the save policy's backward runs in time pieces (6 chunks, the last ragged).
+    dbeta is formed undivided (<k_i gamma_i, E_bar_i> + <v_i, P_i>), so it stays finite and exact
+    at beta = 0 ("ReWY" paper, numerical coverage: zero and tiny beta)."""
+    case = make_case(io="bf16", gate=gate, B=2, T=330, H=2, K=128, V=128, seed=10, beta_mode=mode)
+    got = packed_np(case, gpu_run(case, policy=policy))
+    errs = compare_full(case, got, run_oracle(case), TOL["bf16"])
+    record_errors(f"beta_{mode}:{gate}:{'save' if policy else 'recompute'}", errs, tol=TOL["bf16"])
+
+
 @pytest.mark.parametrize("io,D,H", [("fp32", 64, 2), ("bf16", 128, 2), ("bf16", 128, 48)])
 def test_policies_agree_and_runs_are_deterministic(io, D, H):
     """Repeated runs are bitwise identical (no atomics); the save-intermediates
@@ -246,32 +260,48 @@ def test_cuda_graph_replay_with_new_inputs():
         assert torch.equal(grads[i], ref[name]), name
 
 
-def _sample_pairs(case, n=3):
+def _sample_pairs(case, idx):
+    """(sequence, head) pairs the oracle recomputes at full size: every pair of the tiny workload;
+    otherwise every sequence with heads spread over the head range (16 pairs for the equal-length
+    batches, two heads of each packed sequence, whose lengths all end in a ragged chunk). Each pair
+    spans all of its sequence's chunks, so every time piece of the backward is covered."""
     N, H = case.N, case.H
-    pairs = [(0, 0), (N - 1, H - 1), (N // 2, H // 2)]
+    if idx == 1:
+        return [(n, h) for n in range(N) for h in range(H)]
+    per_seq = max(2, 16 // N)
     out = []
-    for p in pairs:
-        if p not in out:
-            out.append(p)
-    return out[:n]
+    for n in range(N):
+        for j in range(per_seq):
+            h = (n * 5 + j * (H // per_seq) + (H - 1) * (j == per_seq - 1)) % H
+            if (n, h) not in out:
+                out.append((n, h))
+    return out
 
 
+# The benchmark times the save policy with the library's default backward schedule (time pieces for
+# equal-length batches whose reverse scan leaves SMs idle); the recompute policy runs beside it.
+FULL_SIZE_RUNS = [dict(policy=1, schedule=0), dict(policy=0, schedule=0)]
+
+
+@pytest.mark.parametrize("run", FULL_SIZE_RUNS, ids=["save-default-schedule", "recompute"])
 @pytest.mark.parametrize("idx", [1, 2, 3, 4, 5])
-def test_full_size_configs_on_sampled_heads(idx):
-    """The benchmark workloads at full size, in the launch configuration the
-    benchmark times; the oracle recomputes sampled (sequence, head) pairs
-    one by one and every output must be finite everywhere."""
+def test_full_size_configs_on_sampled_heads(idx, run):
+    """The benchmark workloads at full size. The save-policy run is the launch configuration the
+    benchmark times (its forward keeps the intermediates, its backward runs in the library's default
+    schedule); the oracle recomputes sampled (sequence, head) pairs one by one, and every output
+    must be finite everywhere."""
     case = make_config_case(idx)
-    out = gpu_run(case)
+    out = gpu_run(case, policy=run["policy"], schedule=run["schedule"])
     for name, x in out.items():
         if x is not None:
             assert bool(torch.isfinite(x.float()).all()), name
     got = packed_np(case, out)
     del out
-    pairs = _sample_pairs(case) if idx != 1 else [(n, h) for n in range(case.N) for h in range(case.H)]
+    pairs = _sample_pairs(case, idx)
     ref = run_oracle_pairs(case, pairs)
     ss = case.seq_starts
     tol = TOL[CONFIGS[idx]["io"]]
+    errs = {}
     for name in NAMES:
         if name == "dg" and case.gate == "none":
             continue
@@ -282,5 +312,7 @@ def test_full_size_configs_on_sampled_heads(idx):
             else:
                 g_parts.append(got[name][ss[n]:ss[n + 1], h])
             r_parts.append(ref[name][i])
-        check_close(f"config{idx}:{name}", np.concatenate([x.ravel() for x in g_parts]),
-                    np.concatenate([x.ravel() for x in r_parts]), tol)
+        errs[name] = check_close(f"config{idx}:{name}", np.concatenate([x.ravel() for x in g_parts]),
+                                 np.concatenate([x.ravel() for x in r_parts]), tol)
+    record_errors(f"{CONFIGS[idx]['name']}:{'save' if run['policy'] else 'recompute'}", errs,
+                  pairs=len(pairs), tol=tol)
