@@ -77,11 +77,13 @@ def flops_model(case):
 
 
 def kernel_work(case, save=False):
-    """Algorithmic work per launch of each library kernel: dense FLOPs (the
-    products the kernel owns in the FLOP model) and bytes (every tensor the
-    kernel must read or write once, at its stored precision), summed over
-    chunk x head with the exact chunk length n (d = dk = dv). Under the save
-    policy the forward prep also writes A for the backward."""
+    """Work per launch of each library kernel: dense FLOPs (the products the
+    kernel owns in the FLOP model) and STORED bytes (every tensor the kernel
+    must read or write once at its stored precision, the chunk intermediates
+    included), summed over chunk x head with the exact chunk length n
+    (d = dk = dv). Under the save policy the forward prep also writes A for the
+    backward. The roofline's algorithmic bytes (the operator's own inputs,
+    outputs and states only) are in io_bytes."""
     d = case.K
     e = 2 if case.io == "bf16" else 4
     gb = {"channel": 4 * d, "scalar": 4, "none": 0}[case.gate]   # log-decay bytes per token
@@ -115,6 +117,35 @@ def kernel_work(case, save=False):
     for kname in ("k_fwd_scan_tc", "k_bwd_scan_tc"):
         by[kname] += st
     return {k: (fl[k] * case.H, by[k] * case.H) for k in fl}
+
+
+def io_bytes(case):
+    """Algorithmic HBM bytes per launch of each library kernel: only the operator's own inputs,
+    outputs and states that the kernel reads or writes (chunk intermediates excluded), summed over
+    chunk x head with the exact chunk length n. The consumer reads q, k, v, dO, beta, g and writes
+    dq, dk, dv, dbeta, dg; the prep reads q, k, v, beta, g; the output scan writes o and reads h0,
+    writes ht; the reverse scan reads dO and dht and writes dh0."""
+    d = case.K
+    e = 2 if case.io == "bf16" else 4
+    gb = {"channel": 4 * d, "scalar": 4, "none": 0}[case.gate]
+    tok = sum(chunk_lengths(case)) * case.H
+    st = 4 * d * d * case.N * case.H
+    by = {
+        "k_prep_tc": tok * (3 * d * e + e + gb),
+        "k_fwd_scan_tc": tok * d * e + 2 * st,
+        "k_fwd_scan_tc_save": st,
+        "k_fwd_scan_tc_recompute": st,
+        "k_bwd_scan_tc": tok * d * e + 2 * st,
+        "k_bwd_consumer_tc": tok * (4 * d * e + e + gb + 3 * d * e + e + gb),
+    }
+    for k in ("k_prep", "k_fwd_scan", "k_bwd_scan", "k_bwd_dstate", "k_bwd_intra"):
+        by.setdefault(k, 0.0)
+    by["k_prep"] = by["k_prep_tc"]
+    by["k_fwd_scan"] = by["k_fwd_scan_tc"]
+    by["k_bwd_scan"] = by["k_bwd_scan_tc"]
+    by["k_bwd_dstate"] = tok * (2 * d * e + e + d * e)            # v, dO, beta in; dv out
+    by["k_bwd_intra"] = tok * (3 * d * e + e + gb + 2 * d * e + e + gb)   # q, k, dO, beta, g in; dq, dk, dbeta, dg out
+    return by
 
 
 def token_bytes(case):
@@ -349,6 +380,8 @@ def run_ours(args):
     if clocks:
         clocks.start()
         time.sleep(0.3)
+    # eager calls through the public API, every launch bracketed by the library's own events (the
+    # per-kernel times and the roofline come from this region)
     profile_begin(lib)
     t_wall = time.perf_counter()
     for i in range(K):
@@ -362,11 +395,43 @@ def run_ours(args):
     t_wall = time.perf_counter() - t_wall
     barrier()
     kern = profile_end(lib)
-    clk = clocks.stop() if clocks else None
     fwd_ms = [a.elapsed_time(b) for a, b, _ in ev]
     bwd_ms = [b.elapsed_time(c) for _, b, c in ev]
-    step_ms = sum(fwd_ms) / K + sum(bwd_ms) / K
-    step_ms = max_over_ranks(step_ms, ws, dev)
+    eager_ms = [f + b for f, b in zip(fwd_ms, bwd_ms)]
+    # the same step captured once as a CUDA graph and replayed (the pages' timing protocol: graph
+    # replays, medians), L2 flushed before every replay
+    graph_ms = None
+    if not args.no_graph:
+        cap = torch.cuda.Stream(device=dev)
+        cap.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(cap):
+            step()
+        torch.cuda.current_stream().wait_stream(cap)
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            step()
+        for _ in range(args.warmup):
+            gr.replay()
+        torch.cuda.synchronize()
+        barrier()
+        gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        tg = time.perf_counter()
+        for i in range(K):
+            l2.zero_()
+            gev[i][0].record()
+            gr.replay()
+            gev[i][1].record()
+        torch.cuda.synchronize()
+        t_wall += time.perf_counter() - tg
+        barrier()
+        graph_ms = [a.elapsed_time(b) for a, b in gev]
+        del gr
+    clk = clocks.stop() if clocks else None
+    eager_med = statistics.median(eager_ms)
+    graph_med = statistics.median(graph_ms) if graph_ms else None
+    # headline: the median step of the graph replays (eager median when graphs are off); max over ranks
+    step_ms = max_over_ranks(graph_med if graph_med is not None else eager_med, ws, dev)
 
     tokens = case.B * case.T
     fl_f, fl_b, fl_r = flops_model(case)
@@ -375,14 +440,16 @@ def run_ours(args):
     tflops_exec = ws * (fl_f + fl_b + (fl_r if args.policy == "recompute" else 0.0)) / (step_ms * 1e-3) / 1e12
     pk = peaks()
     launches = sum(v[0] for v in kern.values())
-    # dominant kernel and its roofline. With a backward in P time pieces the reverse scan and the
-    # consumer run P launches per step, each over 1/P of the units: their per-launch work and
-    # traffic are a pass's divided by P.
+    # dominant kernel (largest total time per step) and its roofline. With a backward in P time
+    # pieces the reverse scan and the consumer run P launches per step, each over 1/P of the units:
+    # their per-launch work and traffic are a pass's divided by P.
     pieces = max(1, round(kern.get("k_bwd_consumer_tc", (K, 0.0))[0] / K))
     work = kernel_work(case, save=bool(save))
+    iob = io_bytes(case)
     for kname in ("k_bwd_scan_tc", "k_bwd_consumer_tc"):
         if kname in work:
             work[kname] = (work[kname][0] / pieces, work[kname][1] / pieces)
+            iob[kname] = iob[kname] / pieces
 
     def traffic_per_launch(kname):
         tr = traffic_for(kname)
@@ -393,10 +460,12 @@ def run_ours(args):
     if dom:
         n_l, tot = kern[dom]
         avg_ms = tot / n_l
-        fl, by = work.get(dom, (0.0, 0.0))
+        fl, stored = work.get(dom, (0.0, 0.0))
+        by = iob.get(dom, 0.0)
         sm_mhz = clk["sm_mhz"] if clk else pk["sm_max"]
         if "_tc" in dom:
-            # which roofline binds: compare the kernel's time at either peak
+            # which roofline binds: compare the kernel's time at either peak (HBM: the algorithmic
+            # bytes, the operator's own inputs and outputs; tensor: the algorithmic FLOPs)
             t_hbm = by / (pk["hbm"] * 1e9)
             t_tc = fl / (pk["bf16"] * 1e12)
             if t_hbm >= t_tc:
@@ -407,11 +476,17 @@ def run_ours(args):
                 achieved = fl / (avg_ms * 1e-3) / 1e12
                 roof = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 2), "peak": pk["bf16"],
                         "unit": "TFLOP/s", "frac": round(achieved / pk["bf16"], 4)}
+            stored_gbs = stored / (avg_ms * 1e-3) / 1e9
             roof.update({"traffic": traffic_per_launch(dom), "avg_launch_ms": round(avg_ms, 4),
                          "launches_per_step": round(n_l / K, 2),
                          "algorithmic_bytes": by, "algorithmic_flops": fl,
+                         "bytes_note": "algorithmic bytes = the operator's own inputs, outputs and states this "
+                                       "kernel reads or writes; stored bytes add the chunk intermediates",
+                         "stored_bytes": stored, "stored_gbs": round(stored_gbs, 1),
+                         "stored_frac": round(stored_gbs / pk["hbm"], 4),
                          "tensor_frac_of_bf16_peak": round(fl / (avg_ms * 1e-3) / 1e12 / pk["bf16"], 4),
-                         "peak_source": pk["source"] + " (MEASURED_PEAKS.json)", "sm_mhz_under_load": sm_mhz})
+                         "peak_source": pk["source"] + " (MEASURED_PEAKS.json, of measured)",
+                         "sm_mhz_under_load": sm_mhz})
         else:
             alu_peak = 152 * 128 * 2 * pk["sm_max"] * 1e6 / 1e12   # FP32 FMA lanes x 2 x clock
             achieved = fl / (avg_ms * 1e-3) / 1e12
@@ -425,9 +500,12 @@ def run_ours(args):
         rec = {"launches": v[0], "avg_ms": round(v[1] / v[0], 4),
                "share": round(v[1] / max(sum(x[1] for x in kern.values()), 1e-9), 4)}
         if k in work and work[k][1] > 0:
-            gbs = work[k][1] / (v[1] / v[0] * 1e-3) / 1e9
+            t_l = v[1] / v[0] * 1e-3
+            gbs = iob.get(k, 0.0) / t_l / 1e9
+            sgbs = work[k][1] / t_l / 1e9
             rec.update({"algorithmic_gbs": round(gbs, 1), "hbm_frac": round(gbs / pk["hbm"], 4),
-                        "tflops": round(work[k][0] / (v[1] / v[0] * 1e-3) / 1e12, 2)})
+                        "stored_gbs": round(sgbs, 1), "stored_frac": round(sgbs / pk["hbm"], 4),
+                        "tflops": round(work[k][0] / t_l / 1e12, 2)})
         kernels[k] = rec
 
     e2e = None
@@ -454,13 +532,20 @@ def run_ours(args):
                        "rule": ("GatedDeltaNet-2: erase b = 2 sigmoid(N(0,1)) per key channel, write w = "
                                 "sigmoid(N(0,1)) per value channel") if args.gdn2
                        else "delta rule with beta",
-                       "l2": "flushed by a 256 MiB write before every timed step"},
+                       "l2": "flushed by a 256 MiB write before every timed step (eager and graph)"},
             "tflops": round(tflops, 2), "tflops_executed": round(tflops_exec, 2),
             "frac_bf16_peak": round(tflops / pk["bf16"], 4),
             "frac_bf16_peak_sustained": round(tflops / pk["bf16_sus"], 4),
             "hbm_algorithmic_gbs": round(ws * token_bytes(case) / (step_ms * 1e-3) / 1e9, 1),
+            "hbm_frac": round(token_bytes(case) / (step_ms * 1e-3) / 1e9 / pk["hbm"], 4),
+            "hbm_floor_ms": round(token_bytes(case) / (pk["hbm"] * 1e9) * 1e3, 4),
             "peaks_source": pk["source"],
-            "fwd_ms": round(sum(fwd_ms) / K, 4), "bwd_ms": round(sum(bwd_ms) / K, 4),
+            "timing": {"headline": "median of the CUDA-graph replays" if graph_med is not None
+                       else "median of the eager steps",
+                       "graph_median_ms": None if graph_med is None else round(graph_med, 4),
+                       "eager_median_ms": round(eager_med, 4), "eager_mean_ms": round(sum(eager_ms) / K, 4),
+                       "eager_min_ms": round(min(eager_ms), 4), "eager_max_ms": round(max(eager_ms), 4)},
+            "fwd_ms": round(statistics.median(fwd_ms), 4), "bwd_ms": round(statistics.median(bwd_ms), 4),
             "roofline": roof, "kernels": kernels, "gpu_launches": launches,
             "clocks": clk, "e2e": e2e, "cpu_baseline": cpu, "wall_s": round(t_wall, 3),
         }
@@ -569,24 +654,40 @@ def run_e2e(args, case_cpu, dev, kda, K):
 
 
 # ------------------------------------------------------ oracle (CPU) timing
-def oracle_sample(case_cpu, pairs_wanted=None):
-    """A bounded sample of the workload for the CPU oracle: whole (sequence,
-    head) pairs, one per host core by default."""
-    cores = os.cpu_count() or 1
-    npairs = pairs_wanted or min(case_cpu.N * case_cpu.H, max(cores, 1))
-    pairs = [(i % case_cpu.N, (i * 7) % case_cpu.H) for i in range(npairs)]
-    seen = []
-    for p in pairs:
-        if p not in seen:
-            seen.append(p)
-    return seen, cores
+def host_cores():
+    """Host threads the oracle may use (the cores this process may run on)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
 
 
-def time_oracle(case_cpu, pairs, cores):
+def oracle_sample(case_cpu):
+    """The bounded sample both oracle legs time: whole (sequence, head) pairs of the workload, one
+    per host core (all of them when the workload has fewer), spread over sequences and heads."""
+    import math
+    cores = host_cores()
+    N, H = case_cpu.N, case_cpu.H
+    total = N * H
+    npairs = min(total, cores)
+    step = max(1, total // npairs)
+    while math.gcd(step, total) != 1:   # a stride coprime to the pair count visits distinct pairs
+        step += 1
+    pairs = []
+    for j in range(npairs):
+        i = (j * step) % total
+        pairs.append((i % N, i // N))
+    return pairs, cores
+
+
+def time_oracle(case_cpu, pairs, threads, prepared=None):
+    """Wall time of the FP64 oracle (recurrence + BPTT) on the sampled pairs with `threads` host
+    threads; returns (tokens/s, seconds, token-heads). tokens/s = token-heads / H / seconds, the
+    rate at which whole tokens of the workload (all H heads) would be processed."""
     from oracle.cases import pairs_arrays, run_pairs_arrays
-    cat, starts = pairs_arrays(case_cpu, pairs)
+    cat, starts = prepared if prepared is not None else pairs_arrays(case_cpu, pairs)
     t = time.perf_counter()
-    run_pairs_arrays(case_cpu, cat, starts, backward=True, nthreads=cores)
+    run_pairs_arrays(case_cpu, cat, starts, backward=True, nthreads=threads)
     dt = time.perf_counter() - t
     ss = case_cpu.seq_starts
     tok_heads = sum(ss[n + 1] - ss[n] for n, _ in pairs)
@@ -594,13 +695,18 @@ def time_oracle(case_cpu, pairs, cores):
 
 
 def cpu_baseline(case_cpu):
-    # up to four (sequence, head) pairs per host core: the whole kda_bf16 workload
-    # (64 pairs) on 16 cores, some tens of core-seconds
-    pairs, cores = oracle_sample(case_cpu, pairs_wanted=min(case_cpu.N * case_cpu.H, 4 * (os.cpu_count() or 1)))
-    v, dt, th = time_oracle(case_cpu, pairs, cores)
+    """The oracle on the host cores: one (sequence, head) pair per core, all cores; and one pair on
+    one thread (the single-core figure)."""
+    from oracle.cases import pairs_arrays
+    pairs, cores = oracle_sample(case_cpu)
+    prep = pairs_arrays(case_cpu, pairs)
+    v, dt, th = time_oracle(case_cpu, pairs, cores, prep)
+    v1, dt1, th1 = time_oracle(case_cpu, pairs[:1], 1)
     return {"value": round(v, 2), "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"{len(pairs)} whole (sequence, head) pairs = {th} token-heads, fp64 "
-                      f"recurrence + BPTT, {dt:.1f} s wall; tokens/s = token-heads / H / wall"}
+            "sample": f"{len(pairs)} whole (sequence, head) pairs (one per host core) = {th} token-heads, fp64 "
+                      f"recurrence + BPTT, {dt:.2f} s wall on {cores} threads; tokens/s = token-heads / H / wall",
+            "value_1thread": round(v1, 2),
+            "sample_1thread": f"1 pair = {th1} token-heads on 1 thread, {dt1:.2f} s wall"}
 
 
 def with_prologue(case):
@@ -685,33 +791,42 @@ def run_decode(args):
 
 
 def run_reference(args):
+    """The reference arm: the FP64 oracle (the only reference there is), timed on the host cores.
+    Each step runs the same bounded sample as the CPU-baseline leg (one whole (sequence, head)
+    pair per core); ms_per_step is that sample's measured wall time."""
     ws, rank, _ = dist_env()
     if rank != 0:
         return
+    from oracle.cases import pairs_arrays
     from workloads import CONFIGS, make_config_case
     cfg = CONFIGS[args.config]
     case_cpu = make_config_case(args.config)
-    pairs, cores = oracle_sample(case_cpu, pairs_wanted=max(1, min(os.cpu_count() or 1, 8)))
+    pairs, cores = oracle_sample(case_cpu)
+    prep = pairs_arrays(case_cpu, pairs)
     for _ in range(args.warmup):
-        time_oracle(case_cpu, pairs[:1], 1)
+        time_oracle(case_cpu, pairs, cores, prep)
     vals, dts, th = [], [], 0
     for _ in range(args.steps):
-        v, dt, th = time_oracle(case_cpu, pairs, cores)
+        v, dt, th = time_oracle(case_cpu, pairs, cores, prep)
         vals.append(v)
         dts.append(dt)
-    value = statistics.median(vals)
-    sample = (f"{len(pairs)} whole (sequence, head) pairs per step = {th} token-heads of the "
-              f"workload, fp64 recurrence + BPTT on {cores} host threads")
+    dt_med = statistics.median(dts)
+    value = th / case_cpu.H / dt_med
+    v1, dt1, th1 = time_oracle(case_cpu, pairs[:1], 1)
+    sample = (f"{len(pairs)} whole (sequence, head) pairs per step (one per host core) = {th} token-heads of "
+              f"the workload, fp64 recurrence + BPTT on {cores} host threads; ms_per_step = the sample's "
+              f"median wall time; tokens/s = token-heads / H / wall")
     line = {"metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(1e3 * case_cpu.B * case_cpu.T / value, 2),
+            "ms_per_step": round(1e3 * dt_med, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded; shapes and distributions of the workload)",
             "config": {"workload": cfg["name"], "B": case_cpu.B, "T": case_cpu.T, "H": case_cpu.H,
                        "dk": case_cpu.K, "dv": case_cpu.V, "gate": case_cpu.gate, "io": cfg["io"]},
             "impl": "reference",
             "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": cores,
-                             "kind": "oracle", "sample": sample},
+                             "kind": "oracle", "sample": sample, "value_1thread": round(v1, 2),
+                             "sample_1thread": f"1 pair = {th1} token-heads on 1 thread, {dt1:.2f} s wall"},
             "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -720,8 +835,10 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
-    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time eager calls only (no CUDA-graph replay leg)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=WORKLOAD_IDX)
     ap.add_argument("--no-e2e", action="store_true")
