@@ -1247,4 +1247,20 @@ kda_status kda_device_status(const kda_problem* p, const void* ws, size_t ws_byt
     return KDA_OK;
 }
 
+kda_status kda_selftest_device_timeout(const kda_problem* p, void* ws, size_t ws_bytes, unsigned limit_us,
+                                       kda_stream_t stream) {
+    Dims d;
+    kda_status st = check_dims(p, d);
+    if (st != KDA_OK) return st;
+    if (d.Ttot == 0) return fail(KDA_ERR_INVALID_ARG, "the self-test needs a problem with tokens (a chunk table)");
+    if (limit_us < 1 || limit_us > 1000000) return fail(KDA_ERR_INVALID_ARG, "limit_us must be in [1, 1000000]");
+    const Layout L = layout(d);
+    if ((st = check_ws(ws, ws_bytes, L.table)) != KDA_OK) return st;
+    Carver cw{static_cast<char*>(ws)};
+    kda::Table t = carve_table(cw, d);
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = kda::launch_wait_selftest(t, (uint64_t)limit_us * 1000ull, cs);
+    return e == cudaSuccess ? KDA_OK : cuda_fail(e, "timeout self-test");
+}
+
 }  // extern "C"

@@ -187,6 +187,8 @@ void set_last_error(const char* msg);
 
 // --------------------------------------------------------------- launchers
 // Each returns cudaSuccess or the launch error. Defined in the .cu files.
+// Self-test of the device-timeout path (sets bit 1 of t.err after a bounded wait of limit_ns).
+cudaError_t launch_wait_selftest(Table t, uint64_t limit_ns, cudaStream_t st);
 cudaError_t launch_table(const Shape& s, int B, int T, const int32_t* cu, Table t, cudaStream_t st);
 // GatedDeltaNet-2 ("GatedDeltaNet-2 (NVlabs) — official spec transcription", §3):
 // an erase vector b per key channel and a write vector w per value channel take

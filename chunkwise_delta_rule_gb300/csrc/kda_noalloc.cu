@@ -24,7 +24,38 @@ __device__ __align__(256) unsigned char g_noalloc_scratch[KDA_NOALLOC_SCRATCH_BY
 constexpr int kMaxDevices = 64;
 std::atomic<void*> g_scratch_addr[kMaxDevices];
 
+// The scratch's device address on the current device (looked up on the first call made there).
+kda_status scratch_address(void** ws) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        kda::set_last_error((std::string("cudaGetDevice: ") + cudaGetErrorString(e)).c_str());
+        return KDA_ERR_CUDA;
+    }
+    if (dev < 0 || dev >= kMaxDevices) {
+        kda::set_last_error("device index beyond the no-allocation table");
+        return KDA_ERR_UNSUPPORTED;
+    }
+    *ws = g_scratch_addr[dev].load(std::memory_order_acquire);
+    if (!*ws) {
+        e = cudaGetSymbolAddress(ws, g_noalloc_scratch);
+        if (e != cudaSuccess || !*ws) {
+            kda::set_last_error((std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e)).c_str());
+            return KDA_ERR_CUDA;
+        }
+        g_scratch_addr[dev].store(*ws, std::memory_order_release);
+    }
+    return KDA_OK;
+}
+
 }  // namespace
+
+extern "C" kda_status kda_noalloc_device_status(const kda_problem* p, kda_stream_t stream, int32_t* word) {
+    void* ws = nullptr;
+    const kda_status st = scratch_address(&ws);
+    if (st != KDA_OK) return st;
+    return kda_device_status(p, ws, (size_t)KDA_NOALLOC_SCRATCH_BYTES, stream, word);
+}
 
 extern "C" kda_status kda_chunk_fwd_noalloc(const kda_problem* p, void* o, float* ht,
                                              kda_stream_t stream) {
@@ -44,25 +75,9 @@ extern "C" kda_status kda_chunk_fwd_noalloc(const kda_problem* p, void* o, float
                                 .c_str());
         return KDA_ERR_WORKSPACE;
     }
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) {
-        kda::set_last_error((std::string("cudaGetDevice: ") + cudaGetErrorString(e)).c_str());
-        return KDA_ERR_CUDA;
-    }
-    if (dev < 0 || dev >= kMaxDevices) {
-        kda::set_last_error("device index beyond the no-allocation table");
-        return KDA_ERR_UNSUPPORTED;
-    }
-    void* ws = g_scratch_addr[dev].load(std::memory_order_acquire);
-    if (!ws) {
-        e = cudaGetSymbolAddress(&ws, g_noalloc_scratch);
-        if (e != cudaSuccess || !ws) {
-            kda::set_last_error((std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e)).c_str());
-            return KDA_ERR_CUDA;
-        }
-        g_scratch_addr[dev].store(ws, std::memory_order_release);
-    }
+    void* ws = nullptr;
+    const kda_status st = scratch_address(&ws);
+    if (st != KDA_OK) return st;
     // Nothing in the scratch must start at zero: the forward writes every word
     // it reads (chunk table, then the chunk intermediates) within the call.
     return kda_chunk_fwd(p, o, ht, nullptr, ws, (size_t)KDA_NOALLOC_SCRATCH_BYTES, stream);

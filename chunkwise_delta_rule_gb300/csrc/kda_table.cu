@@ -3,6 +3,7 @@
 // from (B, T) for equal-length batches. Chunks restart at every sequence
 // start; the last chunk of a sequence holds the remainder (1..64 tokens).
 #include "kda_internal.cuh"
+#include "tc.cuh"
 
 namespace kda {
 namespace {
@@ -76,7 +77,28 @@ __global__ void __launch_bounds__(TBL_THREADS) k_table(Shape s, int B, int T,
     if (tid == 0) t.err[0] = s_bad ? 1 : 0;
 }
 
+// Self-test of the timeout path: one warp waits, with the library's bounded
+// mbarrier wait, on a barrier that nothing arrives at. The wait gives up after
+// limit_ns and the kernel sets bit 1 of the error word, exactly as a kernel of
+// the pipeline does when one of its waits runs out; no copy or MMA is in
+// flight, so the kernel simply returns.
+__global__ void __launch_bounds__(32) k_wait_selftest(Table t, uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        tc::mbar_init(&bar, 1);
+        tc::fence_mbar_init();
+    }
+    __syncwarp();
+    const bool ok = tc::mbar_wait_for(&bar, 0, limit_ns);
+    if (!__all_sync(0xffffffffu, ok) && threadIdx.x == 0) atomicOr(t.err, 2);
+}
+
 }  // namespace
+
+cudaError_t launch_wait_selftest(Table t, uint64_t limit_ns, cudaStream_t st) {
+    k_wait_selftest<<<1, 32, 0, st>>>(t, limit_ns);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_table(const Shape& s, int B, int T, const int32_t* cu, Table t, cudaStream_t st) {
     k_table<<<1, TBL_THREADS, 0, st>>>(s, B, T, cu, t);

@@ -20,8 +20,18 @@
  *
  * Conventions shared by every entry point:
  *  - All tensor pointers are DEVICE pointers, contiguous, row-major, owned by
- *    the caller. The library never allocates, frees or synchronises; all work
- *    is enqueued on the caller's stream and is asynchronous.
+ *    the caller. The library allocates no device memory for the operator's
+ *    tensors or scratch (every buffer is the caller's), frees nothing and does
+ *    not synchronise; all work is enqueued on the caller's stream and is
+ *    asynchronous. Three things are the library's own: (1) on first use per
+ *    host thread and device, one non-blocking side stream and two events,
+ *    kept until exit, which carry independent launches beside the caller's
+ *    stream and are joined back to it by an event before the call returns;
+ *    (2) while tracing is on (kda_profile_begin), CUDA events created on
+ *    demand and reused; (3) the static device array of
+ *    kda_chunk_fwd_noalloc (see there). kda_device_status and
+ *    kda_noalloc_device_status synchronise the stream they are given; they are
+ *    diagnostics, not part of the fast path.
  *  - Token tensors use the packed token axis: [B*T, H, X] (equal lengths:
  *    sequence b owns tokens b*T .. b*T+T-1; packed: sequence n owns tokens
  *    cu_seqlens[n] .. cu_seqlens[n+1]-1 and B must be 1).
@@ -29,7 +39,9 @@
  *    number of packed sequences.
  *  - Arguments are validated before anything is enqueued; on any error
  *    nothing is written and kda_last_error() describes the problem.
- *  - Supported widths: K == V, both 64 or 128.
+ *  - Widths: the chunked calls take any K <= 128 and V <= 4096 (K = V = 64 or
+ *    128 natively, other widths zero-padded, V above 128 as value blocks; see
+ *    kda_problem); the token-by-token call also takes K = 160, 192 and 256.
  */
 #ifndef KDA_H_
 #define KDA_H_
@@ -175,9 +187,19 @@ kda_status kda_chunk_bwd(const kda_problem *p, const void *dout, const float *dh
  * - Sharing: every call on a device uses the same array, which keeps the last
  *   call's contents; calls whose GPU work overlaps (other streams, other host
  *   threads) race on it and must be serialised by the caller. No word of the
- *   array needs to start at zero: the forward writes all it reads. */
+ *   array needs to start at zero: the forward writes all it reads.
+ * - Device errors: the error word lives in the array; read it with
+ *   kda_noalloc_device_status. */
 #define KDA_NOALLOC_SCRATCH_BYTES (32u << 20)
 kda_status kda_chunk_fwd_noalloc(const kda_problem *p, void *o, float *ht, kda_stream_t stream);
+
+/* Error word of the last kda_chunk_fwd_noalloc call on the current device, read
+ * from the library's static array: synchronises `stream`, then reports as
+ * kda_device_status does (KDA_OK when clear, KDA_ERR_DEVICE_TIMEOUT when a
+ * bounded wait inside a kernel gave up, KDA_ERR_INVALID_ARG when cu_seqlens
+ * was inconsistent). `p` must describe the problem of that call. The pages
+ * have no counterpart to this entry point. */
+kda_status kda_noalloc_device_status(const kda_problem *p, kda_stream_t stream, int32_t *word);
 
 /* Token-by-token forward for decoding and short prompts ("Kimi Delta
  * Attention" derivation blog, §4 boxed KDA update; the fused recurrent form):
@@ -200,6 +222,20 @@ kda_status kda_recurrent_fwd(const kda_problem *p, void *o, float *ht, int32_t *
  * KDA_ERR_INVALID_ARG. For diagnostics; the fast path never calls it. */
 kda_status kda_device_status(const kda_problem *p, const void *ws, size_t ws_bytes,
                              kda_stream_t stream, int32_t *word);
+
+/* Self-test of the device-timeout path. Enqueues one small kernel (one warp)
+ * that waits, with the same bounded mbarrier wait every kernel of the library
+ * uses, on a barrier that nothing ever arrives at; after limit_us microseconds
+ * (1 .. 1000000) the wait gives up and the kernel sets bit 1 of the device
+ * error word in `ws` (the word kda_device_status reads for problem p) and
+ * returns. No copy or MMA is in flight during the wait, so the context stays
+ * usable; the next kda_chunk_fwd or kda_chunk_bwd on that workspace rewrites
+ * the word. `ws` needs at least the chunk-table part of the workspace
+ * (kda_workspace_size(p, 0) suffices). The pages have no counterpart to this
+ * entry point: it exists so that the timeout reporting can be tested without
+ * faulting or hanging a GPU. */
+kda_status kda_selftest_device_timeout(const kda_problem *p, void *ws, size_t ws_bytes, unsigned limit_us,
+                                       kda_stream_t stream);
 
 /* Message for the last non-OK status returned on the calling thread
  * (thread-local; "" if none). */

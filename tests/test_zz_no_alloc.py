@@ -53,6 +53,47 @@ def test_noalloc_forward_matches_allocating_forward_twice(kw):
         check_close(f"ht (call {call})", np64(ht), np64(ht_ref), TOL[kw["io"]])
 
 
+def _noalloc_status(lib, p):
+    f = lib.kda_noalloc_device_status
+    f.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]
+    f.restype = ctypes.c_int
+    word = ctypes.c_int32(-1)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    st = f(ctypes.addressof(p.c), stream, ctypes.byref(word))
+    return st, word.value
+
+
+@pytest.mark.parametrize("variant", ["value_blocks", "prologue"])
+def test_noalloc_wider_layouts_match_allocating_forward(variant):
+    """The no-allocation call carves the same sub-layouts as the allocating one: value widths
+    above 128 run as value blocks (split buffers after the core workspace), and the gate
+    activation and q/k normalisation write their buffers after it. Each is compared with
+    kda_chunk_fwd, and the error word read back from the static array is clear."""
+    import chunkwise_delta_rule_gb300 as kda
+    from chunkwise_delta_rule_gb300 import _lib
+    lib = _lib.load()
+    for call, seed in enumerate((81, 82)):
+        if variant == "value_blocks":
+            case = make_case(io="bf16", gate="channel", B=1, T=150, H=2, K=128, V=256, seed=seed).to("cuda")
+            p = kda.make_problem(case.q, case.k, case.v, case.g, case.beta, gate="channel", initial_state=case.h0)
+        else:
+            case = make_case(io="bf16", gate="channel", B=2, T=100, H=2, K=128, V=128, seed=seed).to("cuda")
+            gen = torch.Generator().manual_seed(seed)
+            a_log = torch.log(torch.rand(2, generator=gen) * 3 + 1).cuda()
+            raw_g = torch.randn(case.g.shape, generator=gen).cuda()
+            p = kda.make_problem(case.q * 1.7, case.k * 0.6, case.v, raw_g, case.beta, gate="channel",
+                                 initial_state=case.h0, A_log=a_log, qk_l2norm=True)
+        o_ref, ht_ref, _ = kda.kda_chunk_fwd(p)
+        o = torch.full_like(o_ref, float("nan"))
+        ht = torch.full_like(ht_ref, float("nan"))
+        st = _noalloc(lib, p, o, ht)
+        assert st == 0, _lib.last_error()
+        assert _noalloc_status(lib, p) == (0, 0)
+        torch.cuda.synchronize()
+        check_close(f"o (call {call})", np64(o), np64(o_ref), TOL["bf16"])
+        check_close(f"ht (call {call})", np64(ht), np64(ht_ref), TOL["bf16"])
+
+
 def test_noalloc_rejects_problems_beyond_its_scratch():
     from chunkwise_delta_rule_gb300 import _lib
     lib = _lib.load()
