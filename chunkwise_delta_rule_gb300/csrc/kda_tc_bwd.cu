@@ -373,36 +373,41 @@ __global__ void __launch_bounds__(ST_ALL, 1)
 // Persistent: one CTA per SM walks the (chunk slot, head) units u = c * H + h,
 // u = blockIdx.x, blockIdx.x + gridDim.x, ...; the inputs of the next unit are
 // loaded while this one finishes (three groups, each on its own mbarrier):
-//   C:  k, q (SW128 rows), g (fp32 rows)       after this unit's F2 (last reader of C)
-//   X1: [R ; S], S+bar tile images             after this unit's phase-B MMAs
-//   X2: [dO ; P], v                            after this unit's dg (the F arrays overlap them)
-constexpr int CT = 512;   // 16 warps: four warps share each TMEM lane quarter and split columns
-constexpr int LG = D + 1;
+//   X1: [R ; S], S+bar tile images        } after this unit's phase-B MMAs (the phase-B
+//   X2: [dO ; P], v                        }   operands are the last readers of the X region)
+//   C:  k, q (SW128 rows), g (fp32 rows)  after this unit's key-major epilogue
+// Every accumulator the chain rule reads is key-major (TMEM lane = key k, column = token j), so
+// one pass in registers forms dq, dk, dbeta and G_bar, the reverse in-chunk cumsum runs inside
+// each thread over its tokens, and dq, dk, dg go from registers to HBM.
+constexpr int CT = 512;   // 16 warps: warp w reads TMEM lane quarter w % 4 and token group w / 4
 constexpr int LDR = CT - 32;   // the thread that finds the next unit and issues its loads
-// region X: phase A operands, then phase B operands, then the F-phase arrays
+// region X: phase A operands, then phase B operands
 constexpr int X_RS = 0;          // [R ; S]   bf16 [192][128]  48 KB   (X1)
 constexpr int X_SB = 49152;      // S+bar     bf16 [128][128]  32 KB   (X1)
 constexpr int X_OP = 81920;      // [dO ; P]  bf16 [128][128]  32 KB   (X2)
 constexpr int X_V = 114688;      // v         bf16 [64][128]   16 KB   (X2, SW128 rows)
-constexpr int X_EQ = 0;          // [E_a^T | Q_a^T] tf32 [128][128] 64 KB
-constexpr int X_KZ = 65536;      // (K zeta)^T tf32 [128][64]    32 KB
-constexpr int X_DH = 98304;      // [D ; H_q]^T tf32 [64][128]   32 KB
-constexpr int X_FD = X_OP;       // F phase: sDK [64][129] fp32, then sGQ [64][129] fp32
-constexpr int X_END = X_FD + 2 * BT * LG * 4;
-constexpr int X_SCR = 131072;    // cumsum: segment totals, maxima, minima [3][4][128] fp32 (dead F-array rows)
-constexpr int C_A = (X_END + 1023) & ~1023;       // g (dense rows, as TMA lands them), then alpha
+constexpr int X_EQ = 0;          // [E_a^T | Q_a^T] tf32 [128][128] 64 KB   (rows key k, K = i')
+constexpr int X_DH = 65536;      // [D ; H_q]^T     tf32 [64][128]   32 KB   (rows token j, K = i')
+constexpr int X_BT = 98304;      // [D ; H_q]       tf32 [128][64]   32 KB   (rows i', K = token j)
+constexpr int X_END = 131072;
+constexpr int X_STG = X_END;     // per-warp staging of the transposed bf16 stores, 16 x 512 B
+constexpr int X_SCR = X_END;     // cumsum at the unit start: segment totals, maxima, minima [3][4][128] fp32
+constexpr int C_A = X_STG + 16 * 512;             // g (dense rows, as TMA lands them), then alpha
                                                   // = 2^(G2 - c) at aidx(row, col), fp32 [64][128]
-constexpr int C_K = C_A + 4 * BT * D;             // k bf16 [64][128], SW128 rows (conflict-free row and column reads)
+constexpr int C_K = C_A + 4 * BT * D;             // k bf16 [64][128], SW128 rows
 constexpr int C_Q = C_K + 2 * BT * D;             // q bf16 [64][128], SW128 rows
 constexpr int C_MISC = C_Q + 2 * BT * D;          // small arrays (floats)
-constexpr int M_BETA = 0, M_C2 = 64, M_AL = 192, M_DBW = 448, M_ROWP = 512,
-              M_ENDP = 768, M_ROW = 1280, M_META = 1344, M_ENDT = 1352, M_LAMP = 1480, M_END = 1992;
+constexpr int M_BETA = 0, M_C2 = 64, M_AL = 192, M_DBW = 320, M_ROWP = 384, M_ENDP = 640, M_ROWG = 1152,
+              M_META = 1408, M_LAMP = 1416, M_SEG = 1928, M_ENDQ = 2440, M_END = 2448;
 constexpr int C_BAR = C_MISC + 4 * M_END;
 constexpr int CONS_SMEM = C_BAR + 64 + 1024;
-static_assert(X_SB + D * D * 2 <= X_OP, "X1 tiles overlap the F arrays");
-static_assert(X_V + BT * D * 2 <= X_SCR && X_DH + BT * D * 4 <= X_SCR && X_SCR + 12 * D * 4 <= X_END, "X region");
-static_assert(X_OP % 1024 == 0 && X_V % 1024 == 0 && X_SB % 1024 == 0 && C_K % 1024 == 0 && C_Q % 1024 == 0,
-              "swizzled tiles need 1024-byte alignment");
+// TMEM columns: [H_q ; -D] token-major, then the key-major accumulators (lane = key k, column =
+// token j): S dO^T, S P^T, F_bar^T, T_e^T, T_q^T, T_y^T; (K zeta)^T is the A operand of [T_e ; T_q]^T
+constexpr int T_HD = 0, T_SDO = 64, T_SP = 128, T_FB = 192, T_TE = 256, T_TQ = 320, T_Y = 384, T_KZ = 448;
+static_assert(X_V + BT * D * 2 <= X_END && X_BT + 2 * BT * BT * 4 <= X_END && X_DH + BT * D * 4 <= X_BT, "X region");
+static_assert(X_SCR + 12 * D * 4 <= C_A && X_STG + 16 * 512 <= C_A, "staging region");
+static_assert(X_OP % 1024 == 0 && X_V % 1024 == 0 && X_SB % 1024 == 0 && X_DH % 1024 == 0 && X_BT % 1024 == 0 &&
+              C_A % 1024 == 0 && C_K % 1024 == 0 && C_Q % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 static_assert(CONS_SMEM <= 232448, "consumer shared memory above the per-block limit");
 
 __device__ __forceinline__ float bfx(const bf16* p) { return __bfloat162float(*p); }
@@ -412,9 +417,10 @@ __device__ __forceinline__ float bfx(const bf16* p) { return __bfloat162float(*p
 // lanes fall in distinct banks.
 __device__ __forceinline__ int aidx(int r, int c) { return r * D + (c ^ (r & 31)); }
 
-// Element (r, col) of a [64][128] bf16 tile stored in SW128 rows.
-__device__ __forceinline__ float ldsw(const unsigned char* tile, int r, int col) {
-    return __bfloat162float(*reinterpret_cast<const bf16*>(tile + tc::sw128_off(BT, r, col * 2)));
+// Byte offset of element (token j, key k) in a [64][128] bf16 tile stored in SW128 rows, from the
+// column part kcol = (k / 64) * 64 * 128 + (k % 8) * 2 and the chunk index kch = (k / 8) % 8.
+__device__ __forceinline__ uint32_t swrow(uint32_t kcol, int kch, int j) {
+    return kcol + (uint32_t)(j * 128) + ((uint32_t)(kch ^ (j & 7)) << 4);
 }
 
 // Units of one consumer launch, as an index space i in [0, units): all units (L == 0, i = u), or, for
@@ -506,8 +512,7 @@ template <int GATE, bool GD2>
 __global__ void __launch_bounds__(CT, 1)
     k_bwd_consumer_tc(Shape s, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmo, const __grid_constant__ CUtensorMap tmg,
-                      const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdg,
-                      const bf16* __restrict__ beta,
+                      const __grid_constant__ CUtensorMap tmv, const bf16* __restrict__ beta,
                       const float* __restrict__ g, Table t, FwdTC f, BwdTC bw, bf16* __restrict__ dq,
                       bf16* __restrict__ dk, bf16* __restrict__ dv, bf16* __restrict__ dbeta,
                       float* __restrict__ dg, Gdn2 gd, ConsPiece pc) {
@@ -523,13 +528,12 @@ __global__ void __launch_bounds__(CT, 1)
     float* sAL = sm + M_AL;       // 2^(G2_last - c) per feature
     float* sLamP = sm + M_LAMP;   // [4][128] partial rowsum(S .* S+bar) per key
     float* sDbw = sm + M_DBW;     // <v_i, P_i>
-    float* sRowP = sm + M_ROWP;   // [4][64] partial <k_i, gamma E_bar_i>
-    float* sEndP = sm + M_ENDP;   // [4][128] partial sum_j F_j . F_bar_j
-    float* sRow = sm + M_ROW;     // [64] scalar-gate row sums
-    float* sEndT = sm + M_ENDT;   // [128] endpoint terms of the last row of G_bar
+    float* sRowP = sm + M_ROWP;   // [4][64] partial <k_j, gamma E_bar_j> per lane quarter
+    float* sEndP = sm + M_ENDP;   // [4][128] partial sum_j F_j . F_bar_j per token group
+    float* sRowG = sm + M_ROWG;   // [4][64] scalar gate: partial row sums of G_bar per lane quarter
+    float* sSeg = sm + M_SEG;     // [4][128] per-channel gate: G_bar summed over each token group
+    float* sEndQ = sm + M_ENDQ;   // [4] scalar gate: endpoint terms summed per lane quarter
     int* sMeta = reinterpret_cast<int*>(sm + M_META);             // two slots {unit, n, tok0, -}
-    float* sDK = reinterpret_cast<float*>(base + X_FD);           // [64][129] beta*gamma*E_bar + Y_bar/gamma
-    float* sGQ = sDK + BT * LG;                                   // [64][129] G_bar
     uint64_t* bar = reinterpret_cast<uint64_t*>(base + C_BAR);    // MMA completions
     uint64_t* bldC = bar + 1;                                     // load groups C, X1, X2
     uint64_t* bldX1 = bar + 2;
@@ -544,6 +548,12 @@ __global__ void __launch_bounds__(CT, 1)
     int icur = (int)blockIdx.x, icand = units;   // indices of the current unit and the candidate (thread LDR)
     int nC = 0, nX1 = 0, nX2 = 0;   // load groups issued (thread LDR)
     int wC = 0, wX1 = 0, wX2 = 0;   // load groups waited for (every thread)
+    // this thread's key (TMEM lane) and token group in the key-major passes, and the key's byte
+    // offsets in the k / q tiles
+    const int kr = 32 * quad + lane, jb = 16 * grp;
+    const uint32_t kcol = (uint32_t)((kr >> 6) * BT * 128 + (kr & 7) * 2);
+    const int kch = (kr >> 3) & 7;
+    bf16* stg = reinterpret_cast<bf16*>(base + X_STG + warp * 512);
 
     if (tid == LDR) {
         for (int i = 0; i < 4; ++i) tc::mbar_init(&bar[i], 1);
@@ -569,6 +579,7 @@ __global__ void __launch_bounds__(CT, 1)
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tb = *tslot;
+    const uint32_t tl = tc::taddr(tb, 32 * quad, 0);
     bf16 beta_nx = __float2bfloat16_rn(0.f);   // beta of the next unit (threads < BT), read during this one
     int cand = 0, cn = 0, ct0 = 0, cw = 0;   // next-unit candidate and its table entries (thread LDR)
 
@@ -578,7 +589,6 @@ __global__ void __launch_bounds__(CT, 1)
         if (u < 0) break;
         const int n = meta[1], tok0 = meta[2];
         const int c = u / H, h = u - c * H;
-        const size_t ch = (size_t)u;
         if (tid == LDR) {   // the next candidate and its table entries, used after the phase-B MMAs
             icand = claim_next(pc, icur);
             if (icand < units) {
@@ -591,7 +601,7 @@ __global__ void __launch_bounds__(CT, 1)
         const float beta_r =
             (k == 0) ? ((tid < BT && tid < n && !GD2) ? bfx(beta + (size_t)(tok0 + tid) * H + h) : 0.f)
                      : __bfloat162float(beta_nx);
-        // the G tile for a scalar gate (or zeros): tile C_A is free since the previous unit's F2
+        // the G tile for a scalar gate (or zeros): tile C_A is free since the previous unit's epilogue
         if (GATE != 2) {
             for (int idx = tid; idx < BT * D / 4; idx += CT) {
                 const int r = idx >> 5, c4 = (idx & 31) * 4;
@@ -650,32 +660,46 @@ __global__ void __launch_bounds__(CT, 1)
                 break;
             }
         }
-        // TMEM columns: [0,64) [H_q ; -D] -> [H_q ; D] ; [64,192) [dO S^T ; P S^T] ;
-        // [192,256) F_bar^T ; [256,384) [T_q ; T_e] (then the erase part of G_bar, key rows) ;
-        // [384,448) T_y^T
         if (warp == 0) {
             tc::fence_after_sync();
-            // [dO ; P] [R ; S]^T fills columns [0, 192) in one N = 192 pass (warp-uniform
-            // descriptors, one elected lane issuing)
-            const uint32_t i64 = tc::idesc_bf16(128, 64), i192 = tc::idesc_bf16(128, BT + D);
+            // phase A (warp-uniform descriptors, one elected lane issuing):
+            //   [dO ; P] R^T -> [H_q ; -D] (token rows), S [dO ; P]^T -> [S dO^T | S P^T] and
+            //   S+bar R^T -> F_bar^T (key rows); S is rows 64..191 of the [R ; S] tile
+            const uint32_t i64 = tc::idesc_bf16(128, 64), i128 = tc::idesc_bf16(128, 128);
             const uint64_t dOP = tc::sdesc(sb + X_OP), dRS = tc::sdesc(sb + X_RS), dSB = tc::sdesc(sb + X_SB);
+            const uint64_t dS = tc::sdesc(sb + X_RS + BT * 128);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)
-                tc::mma_bf16_w(tb, tc::kstep_k(dOP, D, ks), tc::kstep_k(dRS, BT + D, ks), i192, ks > 0);
+                tc::mma_bf16_w(tb + T_HD, tc::kstep_k(dOP, D, ks), tc::kstep_k(dRS, BT + D, ks), i64, ks > 0);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)
-                tc::mma_bf16_w(tb + 192, tc::kstep_k(dSB, D, ks), tc::kstep_k(dRS, BT + D, ks), i64, ks > 0);
+                tc::mma_bf16_w(tb + T_SDO, tc::kstep_k(dS, BT + D, ks), tc::kstep_k(dOP, D, ks), i128, ks > 0);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+                tc::mma_bf16_w(tb + T_FB, tc::kstep_k(dSB, D, ks), tc::kstep_k(dRS, BT + D, ks), i64, ks > 0);
             tc::mma_commit_w(bar);
         }
-        // while the MMAs run: rowsum(S .* S+bar) (key kr, a quarter of the values per thread) and
-        // <v_i, P_i>, dv = beta P from the staged tiles
+        // while the MMAs run: (K zeta)^T into TMEM (the A operand of [T_e ; T_q]^T; this thread's
+        // key and 16 tokens, zero past the chunk end; zeta = 1/alpha, unit without a per-channel
+        // gate), rowsum(S .* S+bar) (key kr, a quarter of the values per thread) and <v_i, P_i>,
+        // dv = beta P from the staged tiles
         {
-            const int kr = tid & (D - 1), q4 = tid >> 7;
+            float kz[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const int j = jb + e;
+                const float kv = __bfloat162float(*reinterpret_cast<const bf16*>(sK + swrow(kcol, kch, j)));
+                kz[e] = (j < n) ? ((GATE == 2) ? kv * tc::rcp_approx(sA[aidx(j, kr)]) : kv) : 0.f;
+            }
+            tc::tmem_st16(tl + T_KZ + jb, kz);
+        }
+        {
+            const int kq = tid & (D - 1), q4 = tid >> 7;
             float a0 = 0.f, a1 = 0.f;
 #pragma unroll
             for (int cc = 4 * q4; cc < 4 * q4 + 4; ++cc) {
-                const uint4 a = *reinterpret_cast<const uint4*>(base + X_RS + tc::sw128_off(BT + D, BT + kr, cc * 16));
-                const uint4 bb = *reinterpret_cast<const uint4*>(base + X_SB + tc::sw128_off(D, kr, cc * 16));
+                const uint4 a = *reinterpret_cast<const uint4*>(base + X_RS + tc::sw128_off(BT + D, BT + kq, cc * 16));
+                const uint4 bb = *reinterpret_cast<const uint4*>(base + X_SB + tc::sw128_off(D, kq, cc * 16));
                 const bf16* pa = reinterpret_cast<const bf16*>(&a);
                 const bf16* pb = reinterpret_cast<const bf16*>(&bb);
 #pragma unroll
@@ -684,7 +708,7 @@ __global__ void __launch_bounds__(CT, 1)
                     a1 = fmaf(__bfloat162float(pa[e + 1]), __bfloat162float(pb[e + 1]), a1);
                 }
             }
-            sLamP[q4 * D + kr] = a0 + a1;
+            sLamP[q4 * D + kq] = a0 + a1;
         }
 #pragma unroll
         for (int uu = 0; uu < BT * 16 / CT; ++uu) {   // 16 threads per row, 8 values each
@@ -724,19 +748,21 @@ __global__ void __launch_bounds__(CT, 1)
             for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o, 16);
             if (cc == 0) sDbw[r] = acc;
         }
+        tc::tmem_wait_st();
+        tc::fence_before_sync();
         if (!wait_all(bar, 0, t.err)) break;
         tc::fence_after_sync();
         // ---- epilogue A: mask [H_q ; -D] into [H_q ; D] (scalar gate: fold the pairwise decay
-        // alpha_i / alpha_j), keep it in TMEM as the A operand of [T_q ; T_e], and write its
-        // transpose as the B operand of T_y^T
+        // alpha_i / alpha_j) and write it twice as tf32 operands: [D ; H_q] (rows i', K = token j,
+        // the B operand of [T_e ; T_q]^T) and its transpose (the B operand of T_y^T)
         {
             const int row = 32 * quad + lane, cb0 = grp * 16;
-            const uint32_t ta = tc::taddr(tb, 32 * quad, cb0);
             float a[16];
-            tc::tmem_ld16(ta, a);
+            tc::tmem_ld16(tc::taddr(tb + T_HD, 32 * quad, cb0), a);
             tc::tmem_wait_ld();
             const bool isH = row < BT;
             const int i = isH ? row : row - BT;
+            const int kidx = isH ? BT + i : i;   // row of [D ; H_q]: D rows first, then H_q rows
             const float ai = sA[aidx(i, 0)];
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
@@ -744,40 +770,36 @@ __global__ void __launch_bounds__(CT, 1)
                 float x = (i < n && (isH ? j <= i : j < i)) ? (isH ? a[jj] : -a[jj]) : 0.f;
                 if (GATE == 1) x *= fminf(ai * tc::rcp_approx(sA[aidx(j, 0)]), 1.f);
                 a[jj] = x;
-                const int kidx = isH ? BT + i : i;   // K order of T_y^T: D rows first, then H_q rows
                 *reinterpret_cast<float*>(base + X_DH + tc::sw128_off(BT, j, kidx * 4)) = x;
             }
-            tc::tmem_st16(ta, a);
-            tc::tmem_wait_st();
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+                *reinterpret_cast<float4*>(base + X_BT + tc::sw128_off(2 * BT, kidx, (cb0 + 4 * m) * 4)) =
+                    make_float4(a[4 * m], a[4 * m + 1], a[4 * m + 2], a[4 * m + 3]);
         }
-        // (K zeta)^T (rows = key k, K = token j; zeta = 1/alpha, unit without a per-channel gate) and
-        // [E_alpha^T | Q_alpha^T] (rows = key k, K = token: E part, then Q part), one pass: each
-        // thread owns key kr and four groups of four tokens; rows past the chunk end are zero
+        // [E_alpha^T | Q_alpha^T] (rows = key kr, K = token: E part, then Q part): this thread's key
+        // and 16 tokens, four at a time; rows past the chunk end are zero
         {
-            const int kr = tid & (D - 1), kch = (kr >> 3) & 7;
-            const uint32_t kbase = (uint32_t)((kr >> 6) * BT * 128 + (kr & 7) * 2);
 #pragma unroll
             for (int uq = 0; uq < 4; ++uq) {
-                const int gq = (tid >> 7) + 4 * uq;   // tokens 4gq .. 4gq+3
-                float kz[4], ea[4], qa[4];
+                float ea[4], qa[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const int j = 4 * gq + e;
-                    const uint32_t off = kbase + j * 128 + ((kch ^ (j & 7)) << 4);
+                    const int j = jb + 4 * uq + e;
+                    const uint32_t off = swrow(kcol, kch, j);
                     const float kv = __bfloat162float(*reinterpret_cast<const bf16*>(sK + off));
                     const float qv = __bfloat162float(*reinterpret_cast<const bf16*>(sQ + off));
                     const float al = (GATE == 2) ? sA[aidx(j, kr)] : 1.f;
                     const bool in = j < n;
-                    kz[e] = in ? ((GATE == 2) ? kv * tc::rcp_approx(al) : kv) : 0.f;
                     const float eb = GD2 ? (in ? bfx(static_cast<const bf16*>(gd.erase) +
-                                                          ((size_t)(tok0 + j) * H + h) * D + kr) : 0.f)
-                                              : sBeta[j];
+                                                     ((size_t)(tok0 + j) * H + h) * D + kr) : 0.f)
+                                         : sBeta[j];
                     ea[e] = in ? eb * kv * al : 0.f;
                     qa[e] = in ? scale * qv * al : 0.f;
                 }
-                *reinterpret_cast<float4*>(base + X_KZ + tc::sw128_off(D, kr, gq * 16)) = make_float4(kz[0], kz[1], kz[2], kz[3]);
-                *reinterpret_cast<float4*>(base + X_EQ + tc::sw128_off(D, kr, gq * 16)) = make_float4(ea[0], ea[1], ea[2], ea[3]);
-                *reinterpret_cast<float4*>(base + X_EQ + tc::sw128_off(D, kr, (16 + gq) * 16)) =
+                *reinterpret_cast<float4*>(base + X_EQ + tc::sw128_off(D, kr, (jb + 4 * uq) * 4)) =
+                    make_float4(ea[0], ea[1], ea[2], ea[3]);
+                *reinterpret_cast<float4*>(base + X_EQ + tc::sw128_off(D, kr, (BT + jb + 4 * uq) * 4)) =
                     make_float4(qa[0], qa[1], qa[2], qa[3]);
             }
         }
@@ -786,23 +808,24 @@ __global__ void __launch_bounds__(CT, 1)
         __syncthreads();
         if (warp == 0) {
             tc::fence_after_sync();
+            // phase B (tf32): [T_e ; T_q]^T = (K zeta)^T [D ; H_q]^T (A from TMEM) and
+            // T_y^T = [E_alpha^T | Q_alpha^T] [D ; H_q]
             const uint32_t i128 = tc::idesc_tf32(128, 128), i64 = tc::idesc_tf32(128, 64);
-            const uint64_t dKZ = tc::sdesc(sb + X_KZ), dEQ = tc::sdesc(sb + X_EQ), dDH = tc::sdesc(sb + X_DH);
+            const uint64_t dBT = tc::sdesc(sb + X_BT), dEQ = tc::sdesc(sb + X_EQ), dDH = tc::sdesc(sb + X_DH);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)
-                tc::mma_tf32_ts_w(tb + 256, tb + 8 * ks, tc::kstep_k(dKZ, D, ks), i128, ks > 0);
+                tc::mma_tf32_ts_w(tb + T_TE, tb + T_KZ + 8 * ks, tc::kstep_k(dBT, 2 * BT, ks), i128, ks > 0);
 #pragma unroll
             for (int ks = 0; ks < 16; ++ks)
-                tc::mma_tf32_w(tb + 384, tc::kstep_k(dEQ, D, ks), tc::kstep_k(dDH, BT, ks), i64, ks > 0);
+                tc::mma_tf32_w(tb + T_Y, tc::kstep_k(dEQ, D, ks), tc::kstep_k(dDH, BT, ks), i64, ks > 0);
             tc::mma_commit_w(bar);
         }
         if (!wait_all(bar, 1, t.err)) break;
         tc::fence_after_sync();
         // the next unit: settle it (the candidate, else a walk over the table) and load its
-        // group X1 into the phase-A tiles, free since the phase-B MMAs completed
-        int nxt = -1;
+        // groups X1 and X2 into the X region, free since the phase-B MMAs completed
         if (tid == LDR) {
-            int nn = 0, nt = 0;
+            int nxt = -1, nn = 0, nt = 0;
             if (icand < units && cn > 0 && cw == 0) {
                 nxt = cand;
                 nn = cn;
@@ -818,121 +841,102 @@ __global__ void __launch_bounds__(CT, 1)
             nm[2] = nt;
             if (nxt >= 0) {
                 cons_load_x1(sb, f, bw, (size_t)nxt, bldX1);
+                cons_load_x2(sb, &tmo, &tmv, bw, (size_t)nxt, nxt % H, nt, bldX2);
                 ++nX1;
+                ++nX2;
             }
         }
-        // ---- F1: rows of [T_q ; T_e] and [dO S^T ; P S^T]; four warps per lane quarter, 32 columns
-        // each. Key rows keep the erase part of G_bar in TMEM over the T_e values they consumed
-        // (added to G_bar in F3, where no other thread writes those elements).
-        {
-            const int row = 32 * quad + lane, cb0 = grp * 32;
-            const bool isQ = row < BT;
-            const int i = isQ ? row : row - BT;
-            const float bt = sBeta[i];
-            float part = 0.f;
-            uint32_t packed[16];
-            // q_i (query rows) or k_i (key rows), columns cb0..cb0+31: four 16-byte chunks
-            uint4 xr4[4];
+        // ---- key-major epilogue: key kr, tokens jb .. jb+15 in two halves of 8, later half first
+        // (the reverse cumsum runs inside the thread). With gamma = alpha 2^c:
+        //   gamma Q_g_bar = fac T_q + gamma (dO S^T),  dq = s gamma Q_g_bar
+        //   gamma E_bar   = fac T_e - gamma (P S^T),   dk = beta gamma E_bar + Y_bar / gamma
+        //   Y_bar / gamma = zeta T_y + (lambda / gamma) F_bar
+        //   G_bar = s q gamma Q_g_bar + beta k gamma E_bar - k Y_bar / gamma
+        // (fac = alpha, zeta = 1 / alpha for a per-channel gate; unit otherwise)
+        const float c2k = sC2[kr], alk = sAL[kr];
+        float gx[16];   // per-channel gate: in-group suffix sums of G_bar
+        float run = 0.f, endp = 0.f;
+#pragma unroll
+        for (int h2 = 1; h2 >= 0; --h2) {
+            const int j0 = jb + 8 * h2;
+            const int nrow = min(max(n - j0, 0), 8);
+            float kvs[8], als[8], dkv[8], gb[8];
             {
-                const unsigned char* src = isQ ? sQ : sK;
-#pragma unroll
-                for (int qq = 0; qq < 4; ++qq)
-                    xr4[qq] = *reinterpret_cast<const uint4*>(src + tc::sw128_off(BT, i, (cb0 + 8 * qq) * 2));
-            }
-            const bf16* xv = reinterpret_cast<const bf16*>(xr4);
-#pragma unroll
-            for (int cb = 0; cb < 32; cb += 16) {
-                float tq[16], tp[16];
-                // GatedDeltaNet-2 key rows: the erase vector on columns cb0+cb.. of token i
-                uint4 eb4[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
-                if (GD2 && !isQ && i < n) {
-                    const uint4* ep = reinterpret_cast<const uint4*>(static_cast<const bf16*>(gd.erase) +
-                                                                     ((size_t)(tok0 + i) * H + h) * D + cb0 + cb);
-                    eb4[0] = ep[0];
-                    eb4[1] = ep[1];
-                }
-                const bf16* ebv = reinterpret_cast<const bf16*>(eb4);
-                uint32_t dbw[8];
-                const uint32_t tqa = tc::taddr(tb + 256, 32 * quad, cb0 + cb);
-                tc::tmem_ld16(tqa, tq);
-                tc::tmem_ld16(tc::taddr(tb + 64, 32 * quad, cb0 + cb), tp);
+                float te[8], tq[8], tdo[8], tps[8], dqv[8], dbp[8];
+                tc::tmem_ld8(tl + T_TE + j0, te);
+                tc::tmem_ld8(tl + T_TQ + j0, tq);
+                tc::tmem_ld8(tl + T_SDO + j0, tdo);
+                tc::tmem_ld8(tl + T_SP + j0, tps);
                 tc::tmem_wait_ld();
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) {
-                    const int kr = cb0 + cb + jj;
-                    const float al = sA[aidx(i, kr)];
-                    const float fac = (GATE == 2) ? al : 1.f;      // alpha (unit: folded / no gate)
-                    const float gam = al * sC2[kr];                 // gamma = 2^G2
-                    const float xq = __bfloat162float(xv[cb + jj]);
-                    if (isQ) {
-                        const float Qt = fac * tq[jj] + gam * tp[jj];               // gamma * Q_g_bar
-                        sGQ[i * LG + kr] = scale * xq * Qt;
-                        tq[jj] = scale * Qt;
-                    } else {
-                        const float Et = fac * tq[jj] - gam * tp[jj];               // gamma * E_bar
-                        const float kv = xq;
-                        const float be = GD2 ? __bfloat162float(ebv[jj]) : bt;
-                        sDK[i * LG + kr] = be * Et;
-                        tq[jj] = be * kv * Et;                                      // erase part of G_bar
-                        part = fmaf(kv, Et, part);
-                        if (GD2) {   // db = K gamma .* E_bar, packed in pairs (tp[jj] is spent)
-                            if (jj & 1) dbw[jj / 2] = tc::pack_bf16(tp[jj - 1], kv * Et);
-                            else tp[jj] = kv * Et;
-                        }
-                    }
+                for (int e = 0; e < 8; ++e) {
+                    const int j = j0 + e;
+                    const uint32_t off = swrow(kcol, kch, j);
+                    const float kv = __bfloat162float(*reinterpret_cast<const bf16*>(sK + off));
+                    const float qv = __bfloat162float(*reinterpret_cast<const bf16*>(sQ + off));
+                    const float al = sA[aidx(j, kr)];
+                    const float fac = (GATE == 2) ? al : 1.f;
+                    const float gam = al * c2k;
+                    const float Qt = fac * tq[e] + gam * tdo[e];
+                    const float Et = fac * te[e] - gam * tps[e];
+                    const float be = GD2 ? ((j < n) ? bfx(static_cast<const bf16*>(gd.erase) +
+                                                          ((size_t)(tok0 + j) * H + h) * D + kr) : 0.f)
+                                         : sBeta[j];
+                    dqv[e] = scale * Qt;
+                    dkv[e] = be * Et;
+                    dbp[e] = kv * Et;   // <k_j, gamma E_bar_j> term; GatedDeltaNet-2: d erase
+                    gb[e] = scale * qv * Qt + be * kv * Et;
+                    kvs[e] = kv;
+                    als[e] = al;
                 }
-                if (GD2 && !isQ && i < n) {
-                    uint4* dst = reinterpret_cast<uint4*>(static_cast<bf16*>(gd.derase) +
-                                                          ((size_t)(tok0 + i) * H + h) * D + cb0 + cb);
-                    dst[0] = make_uint4(dbw[0], dbw[1], dbw[2], dbw[3]);
-                    dst[1] = make_uint4(dbw[4], dbw[5], dbw[6], dbw[7]);
-                }
-                if (isQ) {
-#pragma unroll
-                    for (int jj = 0; jj < 8; ++jj) packed[cb / 2 + jj] = tc::pack_bf16(tq[2 * jj], tq[2 * jj + 1]);
-                } else if (GATE != 0) {
-                    tc::tmem_st16(tqa, tq);
+                const size_t row0 = ((size_t)(tok0 + j0) * H + h) * D + 32 * quad;
+                tc::warp_store_t8(stg, dqv, dq + row0, (size_t)H * D, nrow, lane);
+                if (GD2) {
+                    tc::warp_store_t8(stg, dbp, static_cast<bf16*>(gd.derase) + row0, (size_t)H * D, nrow, lane);
+                } else {
+                    const float tot = tc::warp_sum8_spread(dbp, lane);
+                    if ((lane & 3) == 0) sRowP[quad * BT + j0 + (lane >> 2)] = tot;
                 }
             }
-            if (isQ) {
-                if (i < n) {
-                    uint4* dst = reinterpret_cast<uint4*>(dq + ((size_t)(tok0 + i) * H + h) * D + cb0);
+            {
+                float ty[8], fb[8];
+                tc::tmem_ld8(tl + T_Y + j0, ty);
+                tc::tmem_ld8(tl + T_FB + j0, fb);
+                tc::tmem_wait_ld();
 #pragma unroll
-                    for (int qq = 0; qq < 4; ++qq)
-                        dst[qq] = make_uint4(packed[4 * qq], packed[4 * qq + 1], packed[4 * qq + 2], packed[4 * qq + 3]);
+                for (int e = 0; e < 8; ++e) {
+                    const int j = j0 + e;
+                    const float rinv = tc::rcp_approx(als[e]);
+                    const float ze = (GATE == 2) ? rinv : 1.f;
+                    const float dec = alk * rinv;                  // lambda / gamma_j
+                    const float Yt = ze * ty[e] + fb[e] * dec;     // Y_bar / gamma
+                    dkv[e] += Yt;
+                    gb[e] -= kvs[e] * Yt;
+                    if (j < n) endp = fmaf(kvs[e] * dec, fb[e], endp);   // F_j . F_bar_j
                 }
-            } else {
-                sRowP[grp * BT + i] = part;
-                if (GATE != 0) tc::tmem_wait_st();
+            }
+            tc::warp_store_t8(stg, dkv, dk + ((size_t)(tok0 + j0) * H + h) * D + 32 * quad, (size_t)H * D, nrow, lane);
+            if (GATE == 2) {
+#pragma unroll
+                for (int e = 7; e >= 0; --e) {
+                    run += (j0 + e < n) ? gb[e] : 0.f;
+                    gx[8 * h2 + e] = run;
+                }
+            } else if (GATE == 1) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) gb[e] = (j0 + e < n) ? gb[e] : 0.f;
+                const float tot = tc::warp_sum8_spread(gb, lane);
+                if ((lane & 3) == 0) sRowG[quad * BT + j0 + (lane >> 2)] = tot;
             }
         }
-        __syncthreads();
-        // ---- F2: T_y^T and F_bar^T rows = key k, columns = token j; 16 columns per warp
-        {
-            const int kr = 32 * quad + lane, cb0 = grp * 16;
-            const float al_last = sAL[kr];
-            float endp = 0.f;
-            float ty[16], fb[16];
-            tc::tmem_ld16(tc::taddr(tb + 384, 32 * quad, cb0), ty);
-            tc::tmem_ld16(tc::taddr(tb + 192, 32 * quad, cb0), fb);
-            tc::tmem_wait_ld();
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj) {
-                const int j = cb0 + jj;
-                const float rinv = tc::rcp_approx(sA[aidx(j, kr)]);
-                const float ze = (GATE == 2) ? rinv : 1.f;
-                const float dec = al_last * rinv;                   // lambda / gamma_j
-                const float Yt = ze * ty[jj] + fb[jj] * dec;        // Y_bar / gamma
-                const float kv = ldsw(sK, j, kr);
-                sDK[j * LG + kr] += Yt;
-                sGQ[j * LG + kr] -= kv * Yt;
-                if (j < n) endp = fmaf(kv * dec, fb[jj], endp);      // F_j . F_bar_j
-            }
+        if (GATE != 0) {
             sEndP[grp * D + kr] = endp;
+            if (GATE == 2) sSeg[grp * D + kr] = run;
         }
+        // every read of k, q, alpha and beta is done: group C of the next unit may land
         tc::fence_async_smem();   // the alpha tile's generic writes before the next g lands by TMA
+        tc::fence_before_sync();
         __syncthreads();
-        // k, q, g of the next unit into their tiles (last read in F2); its beta into registers
         {
             const int* nm = sMeta + 4 * ((k + 1) & 1);
             const int nu = nm[0];
@@ -953,107 +957,44 @@ __global__ void __launch_bounds__(CT, 1)
                 }
             }
         }
-        // ---- F3: dk, dbeta; key rows add the erase part of G_bar; the endpoint terms of the last
-        // row (lambda rowsum(S .* S+bar) + sum_j F_j . F_bar_j), added to it in dg
-        for (int idx = tid; idx < BT * D / 8; idx += CT) {
-            const int r = idx >> 4, cc = idx & 15;
-            if (r < n) {
-                uint32_t pw[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    pw[e] = tc::pack_bf16(sDK[r * LG + cc * 8 + 2 * e], sDK[r * LG + cc * 8 + 2 * e + 1]);
-                *reinterpret_cast<uint4*>(dk + ((size_t)(tok0 + r) * H + h) * D + cc * 8) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
-            }
-        }
-        if (tid < BT && tid < n && !GD2)
+        if (!GD2 && tid < BT && tid < n)
             dbeta[(size_t)(tok0 + tid) * H + h] = __float2bfloat16_rn(sRowP[tid] + sRowP[BT + tid] + sRowP[2 * BT + tid] +
                                                                       sRowP[3 * BT + tid] + sDbw[tid]);
-        if (GATE != 0) {
-            if (tid < D)
-                sEndT[tid] = sAL[tid] * sC2[tid] * (sLamP[tid] + sLamP[D + tid] + sLamP[2 * D + tid] + sLamP[3 * D + tid]) +
-                             sEndP[tid] + sEndP[D + tid] + sEndP[2 * D + tid] + sEndP[3 * D + tid];
-            if (quad >= 2) {
-                const int i = 32 * quad + lane - BT, cb0 = grp * 32;
-                float ge[2][16];
-                tc::tmem_ld16(tc::taddr(tb + 256, 32 * quad, cb0), ge[0]);
-                tc::tmem_ld16(tc::taddr(tb + 256, 32 * quad, cb0 + 16), ge[1]);
-                tc::tmem_wait_ld();
-                if (i < n) {
+        if (GATE == 2) {
+            // the endpoint terms of the last row (lambda rowsum(S .* S+bar) + sum_j F_j . F_bar_j) reach
+            // every earlier row through the reverse cumsum, as do the later token groups' totals
+            float off = alk * c2k * (sLamP[kr] + sLamP[D + kr] + sLamP[2 * D + kr] + sLamP[3 * D + kr]) +
+                        sEndP[kr] + sEndP[D + kr] + sEndP[2 * D + kr] + sEndP[3 * D + kr];
 #pragma unroll
-                    for (int jj = 0; jj < 32; ++jj) sGQ[i * LG + cb0 + jj] += ge[jj >> 4][jj & 15];
-                }
+            for (int g2 = 1; g2 < 4; ++g2)
+                if (g2 > grp) off += sSeg[g2 * D + kr];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const int j = jb + e;
+                if (j < n) dg[((size_t)(tok0 + j) * H + h) * D + kr] = gx[e] + off;
             }
-            __syncthreads();
-            if (GATE == 2) {
-                // reverse in-chunk cumsum, one feature per lane and 4 segments of 16 rows (warps
-                // 4s..4s+3); segment totals through shared memory (the endpoint partials are
-                // consumed), so each row of dg is written by one warp as 512 contiguous bytes
-                const int col = tid & (D - 1), seg = tid >> 7;
-                float x[16];
-                float acc = 0.f;
+        } else if (GATE == 1) {
+            // scalar gate: dg_j = sum over j' >= j of the feature sums of G_bar, plus the endpoint
+            // terms summed over features
+            if (warp < 4) {
+                float e = alk * c2k * (sLamP[kr] + sLamP[D + kr] + sLamP[2 * D + kr] + sLamP[3 * D + kr]) +
+                          sEndP[kr] + sEndP[D + kr] + sEndP[2 * D + kr] + sEndP[3 * D + kr];
 #pragma unroll
-                for (int r = 15; r >= 0; --r) {
-                    const int row = 16 * seg + r;
-                    acc += (row < n) ? sGQ[row * LG + col] + (row == n - 1 ? sEndT[col] : 0.f) : 0.f;
-                    x[r] = acc;
-                }
-                float* sSeg = sEndP;   // [4][128]
-                sSeg[seg * D + col] = acc;
-                __syncthreads();
-                float off = 0.f;   // sum of the later segments
-                for (int s2 = seg + 1; s2 < 4; ++s2) off += sSeg[s2 * D + col];
-                if (n == BT) {
-                    // a full chunk: dg as a dense [64][128] fp32 tile over the spent dk array, written
-                    // by one TMA store after the unit's last barrier (the load/store pipe stays free)
-                    float* stg = reinterpret_cast<float*>(base + X_FD);
-#pragma unroll
-                    for (int r = 0; r < 16; ++r) stg[(16 * seg + r) * D + col] = x[r] + off;
-                } else {
-#pragma unroll
-                    for (int r = 0; r < 16; ++r) {
-                        const int row = 16 * seg + r;
-                        if (row < n) dg[((size_t)(tok0 + row) * H + h) * D + col] = x[r] + off;
-                    }
-                }
-            } else {
-                for (int r = warp; r < BT; r += CT / 32) {
-                    float xs = 0.f;
-                    for (int col = lane; col < D; col += 32) xs += sGQ[r * LG + col] + (r == n - 1 ? sEndT[col] : 0.f);
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) xs += __shfl_xor_sync(0xffffffffu, xs, o);
-                    if (lane == 0) sRow[r] = xs;
-                }
-                __syncthreads();
+                for (int o = 16; o > 0; o >>= 1) e += __shfl_xor_sync(0xffffffffu, e, o);
+                if (lane == 0) sEndQ[quad] = e;
+                tc::named_sync(1, 128);
                 if (tid == 0) {
-                    float acc = 0.f;
+                    float acc = sEndQ[0] + sEndQ[1] + sEndQ[2] + sEndQ[3];
                     for (int r = n - 1; r >= 0; --r) {
-                        acc += sRow[r];
+                        acc += sRowG[r] + sRowG[BT + r] + sRowG[2 * BT + r] + sRowG[3 * BT + r];
                         dg[(size_t)(tok0 + r) * H + h] = acc;
                     }
                 }
             }
         }
-        // every read of the F arrays is done: group X2 of the next unit lands over them
-        tc::fence_async_smem();
-        tc::fence_before_sync();
-        __syncthreads();
-        if (tid == LDR) {
-            if (GATE == 2 && n == BT) {   // dg of a full chunk from its staging tile; read before X2 lands
-                tc::tma_store3(&tmdg, 0, h, tok0, sb + X_FD);
-                tc::bulk_commit();
-                tc::bulk_wait_read();
-            }
-            const int* nm = sMeta + 4 * ((k + 1) & 1);
-            if (nm[0] >= 0) {
-                cons_load_x2(sb, &tmo, &tmv, bw, (size_t)nm[0], nm[0] % H, nm[2], bldX2);
-                ++nX2;
-            }
-        }
     }
-    // a load still in flight (only after a timeout) lands before the CTA leaves; the last dg store
-    // completes
+    // a load still in flight (only after a timeout) lands before the CTA leaves
     if (tid == LDR) {
-        tc::bulk_wait_all();
         for (; wC < nC; ++wC) tc::mbar_wait(bldC, wC & 1);
         for (; wX1 < nX1; ++wX1) tc::mbar_wait(bldX1, wX1 & 1);
         for (; wX2 < nX2; ++wX2) tc::mbar_wait(bldX2, wX2 & 1);
@@ -1069,18 +1010,17 @@ cudaError_t run_consumer(const Shape& s, const void* q, const void* k, const voi
                          void* dv, void* dbeta, float* dg, cudaStream_t st, const Gdn2& gd, const ConsPiece& pc) {
     cudaError_t e = set_smem_once<k_bwd_consumer_tc<GATE, GD2>>(CONS_SMEM);
     if (e != cudaSuccess) return e;
-    CUtensorMap mq, mk, mo, mg, mv, mdg;
+    CUtensorMap mq, mk, mo, mg, mv;
     memset(&mg, 0, sizeof(mg));
-    memset(&mdg, 0, sizeof(mdg));
     if (!tmap_rows_bf16(&mq, q, s.Ttot, s.H, D) || !tmap_rows_bf16(&mk, k, s.Ttot, s.H, D) ||
         !tmap_rows_bf16(&mo, dout, s.Ttot, s.H, D) || !tmap_rows_bf16(&mv, v, s.Ttot, s.H, D) ||
-        (GATE == 2 && (!tmap_rows_f32(&mg, g, s.Ttot, s.H, D) || !tmap_rows_f32(&mdg, dg, s.Ttot, s.H, D))))
+        (GATE == 2 && !tmap_rows_f32(&mg, g, s.Ttot, s.H, D)))
         return cudaErrorInvalidValue;
     const long units = pc.L ? (long)s.N * pc.L * s.H : (long)s.NC * s.H;
     if (units <= 0) return cudaSuccess;
     if (units > 0x7fffffffL) return cudaErrorInvalidValue;
     const int grid = (int)(units < sm_count() ? units : sm_count());   // one CTA per SM, persistent
-    k_bwd_consumer_tc<GATE, GD2><<<grid, CT, CONS_SMEM, st>>>(s, mq, mk, mo, mg, mv, mdg, (const bf16*)beta, g, t, f, b,
+    k_bwd_consumer_tc<GATE, GD2><<<grid, CT, CONS_SMEM, st>>>(s, mq, mk, mo, mg, mv, (const bf16*)beta, g, t, f, b,
                                                          (bf16*)dq, (bf16*)dk, (bf16*)dv, (bf16*)dbeta, dg, gd, pc);
     return cudaGetLastError();
 }

@@ -227,6 +227,15 @@ __device__ __forceinline__ void tmem_ld16(uint32_t a, float (&v)[16]) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
+// 32 lanes x 32 bits, 8 consecutive columns per thread.
+__device__ __forceinline__ void tmem_ld8(uint32_t a, float (&v)[8]) {
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(a));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
 __device__ __forceinline__ void tmem_st16u(uint32_t a, const uint32_t (&v)[16]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
@@ -383,6 +392,45 @@ __device__ __forceinline__ void warp_store_t16_img(__nv_bfloat16* stg, const flo
             *reinterpret_cast<const uint4*>(stg + r * 40 + q * 8);
     }
     __syncwarp();
+}
+
+// A warp holds 8 values per lane (lane t: column t of rows 0..7 of a 8 x 32
+// block, e.g. one key per lane and 8 tokens). Writes the block as 8 rows of 32
+// bf16, dst[r * ld + t] for r < nrows, through a dense per-warp staging tile of
+// 8 x 32 bf16 (512 bytes): one 16-byte store per lane.
+__device__ __forceinline__ void warp_store_t8(__nv_bfloat16* stg, const float (&a)[8], __nv_bfloat16* dst,
+                                              size_t ld, int nrows, int lane) {
+#pragma unroll
+    for (int r = 0; r < 8; ++r) stg[r * 32 + lane] = __float2bfloat16_rn(a[r]);
+    __syncwarp();
+    const int r = lane >> 2, q = lane & 3;
+    if (r < nrows)
+        *reinterpret_cast<uint4*>(dst + (size_t)r * ld + q * 8) = *reinterpret_cast<const uint4*>(stg + r * 32 + q * 8);
+    __syncwarp();
+}
+
+// Sums 8 per-lane values over the 32 lanes of a warp with 9 shuffles: lane t
+// ends with the total of value 4 b4 + 2 b3 + b2 (b_i = bit i of t); the four
+// lanes that share bits 4..2 hold the same total.
+__device__ __forceinline__ float warp_sum8_spread(const float (&v)[8], int lane) {
+    const bool b4 = (lane >> 4) & 1, b3 = (lane >> 3) & 1, b2 = (lane >> 2) & 1;
+    float a4[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float send = b4 ? v[i] : v[4 + i], keep = b4 ? v[4 + i] : v[i];
+        a4[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+    float a2[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const float send = b3 ? a4[i] : a4[2 + i], keep = b3 ? a4[2 + i] : a4[i];
+        a2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+    const float send = b2 ? a2[0] : a2[1], keep = b2 ? a2[1] : a2[0];
+    float a1 = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+    a1 += __shfl_xor_sync(0xffffffffu, a1, 2);
+    a1 += __shfl_xor_sync(0xffffffffu, a1, 1);
+    return a1;
 }
 
 // Approximate reciprocal (the PTX rcp.approx instruction, about 1 ulp); for
