@@ -412,16 +412,40 @@ static_assert(CONS_SMEM <= 232448, "consumer shared memory above the per-block l
 
 __device__ __forceinline__ float bfx(const bf16* p) { return __bfloat162float(*p); }
 
-// Position of alpha(row, col) in its dense [64][128] tile: the column is XORed
-// with the row (mod 32), so reads along a row or along a column by consecutive
-// lanes fall in distinct banks.
-__device__ __forceinline__ int aidx(int r, int c) { return r * D + (c ^ (r & 31)); }
-
 // Byte offset of element (token j, key k) in a [64][128] bf16 tile stored in SW128 rows, from the
 // column part kcol = (k / 64) * 64 * 128 + (k % 8) * 2 and the chunk index kch = (k / 8) % 8.
 __device__ __forceinline__ uint32_t swrow(uint32_t kcol, int kch, int j) {
     return kcol + (uint32_t)(j * 128) + ((uint32_t)(kch ^ (j & 7)) << 4);
 }
+
+// Key-major tiles the cumsum writes over the tiles it has read (each thread writes, and later
+// reads, its own key and 16 tokens): alpha fp32 [128 keys][64 tokens] over the g tile, k and q
+// bf16 [128 keys][64 tokens] over the token-major k and q tiles. Their 16-byte chunks are XORed
+// with the key, so that eight consecutive keys reach distinct bank groups.
+__device__ __forceinline__ int akm4(int kr, int c4) { return kr * BT + ((c4 ^ (kr & 15)) << 2); }   // alpha, tokens 4 c4 ..
+__device__ __forceinline__ int kkm8(int kr, int c8) { return kr * BT + ((c8 ^ (kr & 7)) << 3); }   // bf16, tokens 8 c8 ..
+__device__ __forceinline__ void ld_alpha16(const float* sA, int kr, int grp, float (&al)[16]) {
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        const float4 v = *reinterpret_cast<const float4*>(sA + akm4(kr, 4 * grp + m));
+        al[4 * m] = v.x;
+        al[4 * m + 1] = v.y;
+        al[4 * m + 2] = v.z;
+        al[4 * m + 3] = v.w;
+    }
+}
+__device__ __forceinline__ void ld_bf16x16(const bf16* t, int kr, int grp, uint32_t (&w)[8]) {
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+        const uint4 v = *reinterpret_cast<const uint4*>(t + kkm8(kr, 2 * grp + b));
+        w[4 * b] = v.x;
+        w[4 * b + 1] = v.y;
+        w[4 * b + 2] = v.z;
+        w[4 * b + 3] = v.w;
+    }
+}
+// The low (hi = 0) or high bf16 of a packed pair, as a float.
+__device__ __forceinline__ float bf_lo_hi(uint32_t w, int hi) { return __uint_as_float(hi ? (w & 0xffff0000u) : (w << 16)); }
 
 // Units of one consumer launch, as an index space i in [0, units): all units (L == 0, i = u), or, for
 // a batch of equal-length sequences of `per` chunks each, chunks lo .. lo+L-1 of every sequence
@@ -522,6 +546,8 @@ __global__ void __launch_bounds__(CT, 1)
     float* sA = reinterpret_cast<float*>(base + C_A);
     const unsigned char* sK = base + C_K;
     const unsigned char* sQ = base + C_Q;
+    bf16* sKm = reinterpret_cast<bf16*>(base + C_K);   // the same tiles, key-major after the cumsum
+    bf16* sQm = reinterpret_cast<bf16*>(base + C_Q);
     float* sm = reinterpret_cast<float*>(base + C_MISC);
     float* sBeta = sm + M_BETA;
     float* sC2 = sm + M_C2;       // 2^c per feature
@@ -589,7 +615,8 @@ __global__ void __launch_bounds__(CT, 1)
         if (u < 0) break;
         const int n = meta[1], tok0 = meta[2];
         const int c = u / H, h = u - c * H;
-        if (tid == LDR) {   // the next candidate and its table entries, used after the phase-B MMAs
+        const int* nm = sMeta + 4 * ((k + 1) & 1);   // the next unit, settled below by thread LDR
+        if (tid == LDR) {   // the next candidate and its table entries
             icand = claim_next(pc, icur);
             if (icand < units) {
                 cand = piece_unit(pc, icand, H);
@@ -610,45 +637,6 @@ __global__ void __launch_bounds__(CT, 1)
             }
         }
         if (tid < BT) sBeta[tid] = beta_r;
-        if (!cons_wait(bldC, wC, t.err)) break;
-        // cumsum (4 segments of 16 rows per feature, warps 4s..4s+3 hold segment s, one feature
-        // per lane), anchors, alpha tile (overlaps the X loads); segments meet in shared memory
-        {
-            const int col = tid & (D - 1), seg = tid >> 7;
-            float* xt = reinterpret_cast<float*>(base + X_SCR);   // [3][4][128] totals, maxima, minima
-            float x[16];
-            float acc = 0.f, hi = -INFINITY, lo = INFINITY;
-#pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                const int row = 16 * seg + r;
-                acc += (row < n) ? sA[row * D + col] : 0.f;
-                x[r] = acc * LOG2E;
-                if (row < n) {
-                    hi = fmaxf(hi, x[r]);
-                    lo = fminf(lo, x[r]);
-                }
-            }
-            xt[seg * D + col] = acc * LOG2E;
-            xt[4 * D + seg * D + col] = hi;
-            xt[8 * D + seg * D + col] = lo;
-            __syncthreads();   // (also: every g read before alpha overwrites the tile at swizzled positions)
-            float off = 0.f, run = 0.f, hh = -INFINITY, ll = INFINITY;
-#pragma unroll
-            for (int s2 = 0; s2 < 4; ++s2) {
-                const float ts = xt[s2 * D + col];
-                if (s2 < seg) off = run + ts;
-                hh = fmaxf(hh, xt[4 * D + s2 * D + col] + run);
-                ll = fminf(ll, xt[8 * D + s2 * D + col] + run);
-                run += ts;
-            }
-            const float cc = (GATE == 0) ? 0.f : 0.5f * (hh + ll);
-#pragma unroll
-            for (int r = 0; r < 16; ++r) sA[aidx(16 * seg + r, col)] = exp2f(x[r] + off - cc);
-            if (seg == 0) {
-                sC2[col] = exp2f(cc);
-                sAL[col] = exp2f(run - cc);   // run: G2 at the chunk end
-            }
-        }
         // groups X1 and X2: [R ; S], S+bar, [dO ; P], v
         {
             const bool r1 = tc::mbar_wait(bldX1, wX1 & 1);
@@ -662,7 +650,8 @@ __global__ void __launch_bounds__(CT, 1)
         }
         if (warp == 0) {
             tc::fence_after_sync();
-            // phase A (warp-uniform descriptors, one elected lane issuing):
+            // phase A (warp-uniform descriptors, one elected lane issuing); it needs only the X
+            // tiles, so it runs under the rowsum, dv and cumsum passes:
             //   [dO ; P] R^T -> [H_q ; -D] (token rows), S [dO ; P]^T -> [S dO^T | S P^T] and
             //   S+bar R^T -> F_bar^T (key rows); S is rows 64..191 of the [R ; S] tile
             const uint32_t i64 = tc::idesc_bf16(128, 64), i128 = tc::idesc_bf16(128, 128);
@@ -679,20 +668,26 @@ __global__ void __launch_bounds__(CT, 1)
                 tc::mma_bf16_w(tb + T_FB, tc::kstep_k(dSB, D, ks), tc::kstep_k(dRS, BT + D, ks), i64, ks > 0);
             tc::mma_commit_w(bar);
         }
-        // while the MMAs run: (K zeta)^T into TMEM (the A operand of [T_e ; T_q]^T; this thread's
-        // key and 16 tokens, zero past the chunk end; zeta = 1/alpha, unit without a per-channel
-        // gate), rowsum(S .* S+bar) (key kr, a quarter of the values per thread) and <v_i, P_i>,
-        // dv = beta P from the staged tiles
-        {
-            float kz[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const int j = jb + e;
-                const float kv = __bfloat162float(*reinterpret_cast<const bf16*>(sK + swrow(kcol, kch, j)));
-                kz[e] = (j < n) ? ((GATE == 2) ? kv * tc::rcp_approx(sA[aidx(j, kr)]) : kv) : 0.f;
+        // the next unit: the candidate, else a walk over the table; every thread sees it after the
+        // wait for group C below
+        if (tid == LDR) {
+            int nxt = -1, nn = 0, nt = 0;
+            if (icand < units && cn > 0 && cw == 0) {
+                nxt = cand;
+                nn = cn;
+                nt = ct0;
+                icur = icand;
+            } else if (icand < units) {
+                icur = claim_next(pc, icand);
+                nxt = cons_find<GATE>(icur, units, pc, H, t, f, nn, nt);
             }
-            tc::tmem_st16(tl + T_KZ + jb, kz);
+            int* wm = sMeta + 4 * ((k + 1) & 1);
+            wm[0] = nxt;
+            wm[1] = nn;
+            wm[2] = nt;
         }
+        // rowsum(S .* S+bar) (key kq, a quarter of the values per thread), <v_i, P_i> and
+        // dv = beta P from the staged tiles, while group C lands
         {
             const int kq = tid & (D - 1), q4 = tid >> 7;
             float a0 = 0.f, a1 = 0.f;
@@ -748,9 +743,93 @@ __global__ void __launch_bounds__(CT, 1)
             for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o, 16);
             if (cc == 0) sDbw[r] = acc;
         }
+        if (!cons_wait(bldC, wC, t.err)) break;
+        // the next unit's beta, kept as bf16 in a register so that the load stays in flight until
+        // that unit starts; GatedDeltaNet-2: its erase and write rows (two 128-byte lines each)
+        // into L2, so that its direct loads of them find them there
+        if (nm[0] >= 0) {
+            const int nh = nm[0] % H;
+            if (tid < BT)
+                beta_nx = (tid < nm[1] && !GD2) ? beta[(size_t)(nm[2] + tid) * H + nh] : __float2bfloat16_rn(0.f);
+            if (GD2 && (tid >> 2) < nm[1]) {
+                const bf16* vec = static_cast<const bf16*>((tid & 2) ? gd.write : gd.erase);
+                tc::prefetch_l2(vec + ((size_t)(nm[2] + (tid >> 2)) * H + nh) * D + (tid & 1) * 64);
+            }
+        }
+        // cumsum (4 segments of 16 rows per feature: thread = key kr, rows jb .. jb+15, the same
+        // key and tokens this thread handles in every later pass), anchors, alpha; segments meet
+        // in shared memory. alpha, k and q are then rewritten key-major over their own tiles.
+        {
+            float* xt = reinterpret_cast<float*>(base + X_SCR);   // [3][4][128] totals, maxima, minima
+            float x[16];
+            float acc = 0.f, hi = -INFINITY, lo = INFINITY;
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                const int row = jb + r;
+                acc += (row < n) ? sA[row * D + kr] : 0.f;
+                x[r] = acc * LOG2E;
+                if (row < n) {
+                    hi = fmaxf(hi, x[r]);
+                    lo = fminf(lo, x[r]);
+                }
+            }
+            uint32_t kk[8], qq[8];   // k and q of this key for the 16 rows, bf16 pairs
+#pragma unroll
+            for (int r = 0; r < 16; r += 2) {
+                const uint32_t o0 = swrow(kcol, kch, jb + r), o1 = swrow(kcol, kch, jb + r + 1);
+                kk[r / 2] = (uint32_t)*reinterpret_cast<const uint16_t*>(sK + o0) |
+                            ((uint32_t)*reinterpret_cast<const uint16_t*>(sK + o1) << 16);
+                qq[r / 2] = (uint32_t)*reinterpret_cast<const uint16_t*>(sQ + o0) |
+                            ((uint32_t)*reinterpret_cast<const uint16_t*>(sQ + o1) << 16);
+            }
+            xt[grp * D + kr] = acc * LOG2E;
+            xt[4 * D + grp * D + kr] = hi;
+            xt[8 * D + grp * D + kr] = lo;
+            __syncthreads();   // (also: every g, k, q read before the key-major tiles overwrite them)
+            float off = 0.f, run = 0.f, hh = -INFINITY, ll = INFINITY;
+#pragma unroll
+            for (int s2 = 0; s2 < 4; ++s2) {
+                const float ts = xt[s2 * D + kr];
+                if (s2 < grp) off = run + ts;
+                hh = fmaxf(hh, xt[4 * D + s2 * D + kr] + run);
+                ll = fminf(ll, xt[8 * D + s2 * D + kr] + run);
+                run += ts;
+            }
+            const float cc = (GATE == 0) ? 0.f : 0.5f * (hh + ll);
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+                *reinterpret_cast<float4*>(sA + akm4(kr, 4 * grp + m)) =
+                    make_float4(exp2f(x[4 * m] + off - cc), exp2f(x[4 * m + 1] + off - cc),
+                                exp2f(x[4 * m + 2] + off - cc), exp2f(x[4 * m + 3] + off - cc));
+#pragma unroll
+            for (int b2 = 0; b2 < 2; ++b2) {
+                *reinterpret_cast<uint4*>(sKm + kkm8(kr, 2 * grp + b2)) =
+                    make_uint4(kk[4 * b2], kk[4 * b2 + 1], kk[4 * b2 + 2], kk[4 * b2 + 3]);
+                *reinterpret_cast<uint4*>(sQm + kkm8(kr, 2 * grp + b2)) =
+                    make_uint4(qq[4 * b2], qq[4 * b2 + 1], qq[4 * b2 + 2], qq[4 * b2 + 3]);
+            }
+            if (grp == 0) {
+                sC2[kr] = exp2f(cc);
+                sAL[kr] = exp2f(run - cc);   // run: G2 at the chunk end
+            }
+        }
+        // (K zeta)^T into TMEM (the A operand of [T_e ; T_q]^T; this thread's key and 16 tokens,
+        // zero past the chunk end; zeta = 1/alpha, unit without a per-channel gate)
+        {
+            float al[16], kz[16];
+            uint32_t kw[8];
+            ld_alpha16(sA, kr, grp, al);
+            ld_bf16x16(sKm, kr, grp, kw);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const float kv = bf_lo_hi(kw[e >> 1], e & 1);
+                kz[e] = (jb + e < n) ? ((GATE == 2) ? kv * tc::rcp_approx(al[e]) : kv) : 0.f;
+            }
+            tc::tmem_st16(tl + T_KZ + jb, kz);
+        }
         tc::tmem_wait_st();
         tc::fence_before_sync();
-        if (!wait_all(bar, 0, t.err)) break;
+        if (!wait_all(bar, 0, t.err)) break;   // phase A done; every key-major tile written
         tc::fence_after_sync();
         // ---- epilogue A: mask [H_q ; -D] into [H_q ; D] (scalar gate: fold the pairwise decay
         // alpha_i / alpha_j) and write it twice as tf32 operands: [D ; H_q] (rows i', K = token j,
@@ -763,12 +842,12 @@ __global__ void __launch_bounds__(CT, 1)
             const bool isH = row < BT;
             const int i = isH ? row : row - BT;
             const int kidx = isH ? BT + i : i;   // row of [D ; H_q]: D rows first, then H_q rows
-            const float ai = sA[aidx(i, 0)];
+            const float ai = (GATE == 1) ? sA[akm4(0, i >> 2) + (i & 3)] : 1.f;   // the gate is one per token
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
                 const int j = cb0 + jj;
                 float x = (i < n && (isH ? j <= i : j < i)) ? (isH ? a[jj] : -a[jj]) : 0.f;
-                if (GATE == 1) x *= fminf(ai * tc::rcp_approx(sA[aidx(j, 0)]), 1.f);
+                if (GATE == 1) x *= fminf(ai * tc::rcp_approx(sA[akm4(0, j >> 2) + (j & 3)]), 1.f);
                 a[jj] = x;
                 *reinterpret_cast<float*>(base + X_DH + tc::sw128_off(BT, j, kidx * 4)) = x;
             }
@@ -780,22 +859,28 @@ __global__ void __launch_bounds__(CT, 1)
         // [E_alpha^T | Q_alpha^T] (rows = key kr, K = token: E part, then Q part): this thread's key
         // and 16 tokens, four at a time; rows past the chunk end are zero
         {
+            float al[16];
+            uint32_t kw[8], qw[8];
+            ld_alpha16(sA, kr, grp, al);
+            ld_bf16x16(sKm, kr, grp, kw);
+            ld_bf16x16(sQm, kr, grp, qw);
 #pragma unroll
             for (int uq = 0; uq < 4; ++uq) {
                 float ea[4], qa[4];
+                const float4 b4 = *reinterpret_cast<const float4*>(sBeta + jb + 4 * uq);
+                const float bq[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const int j = jb + 4 * uq + e;
-                    const uint32_t off = swrow(kcol, kch, j);
-                    const float kv = __bfloat162float(*reinterpret_cast<const bf16*>(sK + off));
-                    const float qv = __bfloat162float(*reinterpret_cast<const bf16*>(sQ + off));
-                    const float al = (GATE == 2) ? sA[aidx(j, kr)] : 1.f;
+                    const int q16 = 4 * uq + e, j = jb + q16;
+                    const float kv = bf_lo_hi(kw[q16 >> 1], q16 & 1);
+                    const float qv = bf_lo_hi(qw[q16 >> 1], q16 & 1);
+                    const float av = (GATE == 2) ? al[q16] : 1.f;
                     const bool in = j < n;
                     const float eb = GD2 ? (in ? bfx(static_cast<const bf16*>(gd.erase) +
                                                      ((size_t)(tok0 + j) * H + h) * D + kr) : 0.f)
-                                         : sBeta[j];
-                    ea[e] = in ? eb * kv * al : 0.f;
-                    qa[e] = in ? scale * qv * al : 0.f;
+                                         : bq[e];
+                    ea[e] = in ? eb * kv * av : 0.f;
+                    qa[e] = in ? scale * qv * av : 0.f;
                 }
                 *reinterpret_cast<float4*>(base + X_EQ + tc::sw128_off(D, kr, (jb + 4 * uq) * 4)) =
                     make_float4(ea[0], ea[1], ea[2], ea[3]);
@@ -822,29 +907,12 @@ __global__ void __launch_bounds__(CT, 1)
         }
         if (!wait_all(bar, 1, t.err)) break;
         tc::fence_after_sync();
-        // the next unit: settle it (the candidate, else a walk over the table) and load its
-        // groups X1 and X2 into the X region, free since the phase-B MMAs completed
-        if (tid == LDR) {
-            int nxt = -1, nn = 0, nt = 0;
-            if (icand < units && cn > 0 && cw == 0) {
-                nxt = cand;
-                nn = cn;
-                nt = ct0;
-                icur = icand;
-            } else if (icand < units) {
-                icur = claim_next(pc, icand);
-                nxt = cons_find<GATE>(icur, units, pc, H, t, f, nn, nt);
-            }
-            int* nm = sMeta + 4 * ((k + 1) & 1);
-            nm[0] = nxt;
-            nm[1] = nn;
-            nm[2] = nt;
-            if (nxt >= 0) {
-                cons_load_x1(sb, f, bw, (size_t)nxt, bldX1);
-                cons_load_x2(sb, &tmo, &tmv, bw, (size_t)nxt, nxt % H, nt, bldX2);
-                ++nX1;
-                ++nX2;
-            }
+        // groups X1 and X2 of the next unit into the X region, free since the phase-B MMAs completed
+        if (tid == LDR && nm[0] >= 0) {
+            cons_load_x1(sb, f, bw, (size_t)nm[0], bldX1);
+            cons_load_x2(sb, &tmo, &tmv, bw, (size_t)nm[0], nm[0] % H, nm[2], bldX2);
+            ++nX1;
+            ++nX2;
         }
         // ---- key-major epilogue: key kr, tokens jb .. jb+15 in two halves of 8, later half first
         // (the reverse cumsum runs inside the thread). With gamma = alpha 2^c:
@@ -867,21 +935,29 @@ __global__ void __launch_bounds__(CT, 1)
                 tc::tmem_ld8(tl + T_TQ + j0, tq);
                 tc::tmem_ld8(tl + T_SDO + j0, tdo);
                 tc::tmem_ld8(tl + T_SP + j0, tps);
+                const uint4 k8 = *reinterpret_cast<const uint4*>(sKm + kkm8(kr, 2 * grp + h2));
+                const uint4 q8 = *reinterpret_cast<const uint4*>(sQm + kkm8(kr, 2 * grp + h2));
+                const float4 a0 = *reinterpret_cast<const float4*>(sA + akm4(kr, 4 * grp + 2 * h2));
+                const float4 a1 = *reinterpret_cast<const float4*>(sA + akm4(kr, 4 * grp + 2 * h2 + 1));
+                const float4 b0 = *reinterpret_cast<const float4*>(sBeta + j0);
+                const float4 b1 = *reinterpret_cast<const float4*>(sBeta + j0 + 4);
+                const uint32_t kw[4] = {k8.x, k8.y, k8.z, k8.w}, qw[4] = {q8.x, q8.y, q8.z, q8.w};
+                const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
                 tc::tmem_wait_ld();
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const int j = j0 + e;
-                    const uint32_t off = swrow(kcol, kch, j);
-                    const float kv = __bfloat162float(*reinterpret_cast<const bf16*>(sK + off));
-                    const float qv = __bfloat162float(*reinterpret_cast<const bf16*>(sQ + off));
-                    const float al = sA[aidx(j, kr)];
+                    const float kv = bf_lo_hi(kw[e >> 1], e & 1);
+                    const float qv = bf_lo_hi(qw[e >> 1], e & 1);
+                    const float al = av[e];
                     const float fac = (GATE == 2) ? al : 1.f;
                     const float gam = al * c2k;
                     const float Qt = fac * tq[e] + gam * tdo[e];
                     const float Et = fac * te[e] - gam * tps[e];
                     const float be = GD2 ? ((j < n) ? bfx(static_cast<const bf16*>(gd.erase) +
                                                           ((size_t)(tok0 + j) * H + h) * D + kr) : 0.f)
-                                         : sBeta[j];
+                                         : bv[e];
                     dqv[e] = scale * Qt;
                     dkv[e] = be * Et;
                     dbp[e] = kv * Et;   // <k_j, gamma E_bar_j> term; GatedDeltaNet-2: d erase
@@ -934,28 +1010,12 @@ __global__ void __launch_bounds__(CT, 1)
             if (GATE == 2) sSeg[grp * D + kr] = run;
         }
         // every read of k, q, alpha and beta is done: group C of the next unit may land
-        tc::fence_async_smem();   // the alpha tile's generic writes before the next g lands by TMA
+        tc::fence_async_smem();   // the key-major tiles' generic writes before the next tiles land by TMA
         tc::fence_before_sync();
         __syncthreads();
-        {
-            const int* nm = sMeta + 4 * ((k + 1) & 1);
-            const int nu = nm[0];
-            if (nu >= 0) {
-                const int nh = nu % H;
-                if (tid == LDR) {
-                    cons_load_c<GATE>(sb, &tmk, &tmq, &tmg, nh, nm[2], bldC);
-                    ++nC;
-                }
-                // kept as bf16 so the load stays in flight until the next unit starts
-                if (tid < BT)
-                    beta_nx = (tid < nm[1] && !GD2) ? beta[(size_t)(nm[2] + tid) * H + nh] : __float2bfloat16_rn(0.f);
-                // GatedDeltaNet-2: the next unit's erase and write rows (two 128-byte lines each)
-                // into L2, so that its direct loads of them find them there
-                if (GD2 && (tid >> 2) < nm[1]) {
-                    const bf16* vec = static_cast<const bf16*>((tid & 2) ? gd.write : gd.erase);
-                    tc::prefetch_l2(vec + ((size_t)(nm[2] + (tid >> 2)) * H + nh) * D + (tid & 1) * 64);
-                }
-            }
+        if (tid == LDR && nm[0] >= 0) {
+            cons_load_c<GATE>(sb, &tmk, &tmq, &tmg, nm[0] % H, nm[2], bldC);
+            ++nC;
         }
         if (!GD2 && tid < BT && tid < n)
             dbeta[(size_t)(tok0 + tid) * H + h] = __float2bfloat16_rn(sRowP[tid] + sRowP[BT + tid] + sRowP[2 * BT + tid] +
