@@ -945,25 +945,41 @@ __global__ void __launch_bounds__(CT, 1)
                 const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
                 const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
                 tc::tmem_wait_ld();
+                // pairs of tokens in packed fp32x2 arithmetic
+                const float2 s2 = make_float2(scale, scale), c22 = make_float2(c2k, c2k), nc22 = make_float2(-c2k, -c2k);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
+                for (int e = 0; e < 8; e += 2) {
                     const int j = j0 + e;
-                    const float kv = bf_lo_hi(kw[e >> 1], e & 1);
-                    const float qv = bf_lo_hi(qw[e >> 1], e & 1);
-                    const float al = av[e];
-                    const float fac = (GATE == 2) ? al : 1.f;
-                    const float gam = al * c2k;
-                    const float Qt = fac * tq[e] + gam * tdo[e];
-                    const float Et = fac * te[e] - gam * tps[e];
-                    const float be = GD2 ? ((j < n) ? bfx(static_cast<const bf16*>(gd.erase) +
-                                                          ((size_t)(tok0 + j) * H + h) * D + kr) : 0.f)
-                                         : bv[e];
-                    dqv[e] = scale * Qt;
-                    dkv[e] = be * Et;
-                    dbp[e] = kv * Et;   // <k_j, gamma E_bar_j> term; GatedDeltaNet-2: d erase
-                    gb[e] = scale * qv * Qt + be * kv * Et;
-                    kvs[e] = kv;
-                    als[e] = al;
+                    const float2 kv2 = make_float2(bf_lo_hi(kw[e >> 1], 0), bf_lo_hi(kw[e >> 1], 1));
+                    const float2 qv2 = make_float2(bf_lo_hi(qw[e >> 1], 0), bf_lo_hi(qw[e >> 1], 1));
+                    const float2 al2 = make_float2(av[e], av[e + 1]);
+                    const float2 fac2 = (GATE == 2) ? al2 : make_float2(1.f, 1.f);
+                    const float2 gam2 = __fmul2_rn(al2, c22);
+                    const float2 Qt2 = __ffma2_rn(fac2, make_float2(tq[e], tq[e + 1]),
+                                                  __fmul2_rn(gam2, make_float2(tdo[e], tdo[e + 1])));
+                    const float2 Et2 = __ffma2_rn(fac2, make_float2(te[e], te[e + 1]),
+                                                  __fmul2_rn(__fmul2_rn(al2, nc22), make_float2(tps[e], tps[e + 1])));
+                    float2 be2;
+                    if (GD2) {
+                        const bf16* er = static_cast<const bf16*>(gd.erase) + ((size_t)(tok0 + j) * H + h) * D + kr;
+                        be2 = make_float2((j < n) ? bfx(er) : 0.f, (j + 1 < n) ? bfx(er + (size_t)H * D) : 0.f);
+                    } else {
+                        be2 = make_float2(bv[e], bv[e + 1]);
+                    }
+                    const float2 dq2 = __fmul2_rn(s2, Qt2), dk2 = __fmul2_rn(be2, Et2), db2 = __fmul2_rn(kv2, Et2);
+                    const float2 gb2 = __ffma2_rn(__fmul2_rn(s2, qv2), Qt2, __fmul2_rn(be2, db2));
+                    dqv[e] = dq2.x;
+                    dqv[e + 1] = dq2.y;
+                    dkv[e] = dk2.x;
+                    dkv[e + 1] = dk2.y;
+                    dbp[e] = db2.x;   // <k_j, gamma E_bar_j> term; GatedDeltaNet-2: d erase
+                    dbp[e + 1] = db2.y;
+                    gb[e] = gb2.x;
+                    gb[e + 1] = gb2.y;
+                    kvs[e] = kv2.x;
+                    kvs[e + 1] = kv2.y;
+                    als[e] = al2.x;
+                    als[e + 1] = al2.y;
                 }
                 const size_t row0 = ((size_t)(tok0 + j0) * H + h) * D + 32 * quad;
                 tc::warp_store_t8(stg, dqv, dq + row0, (size_t)H * D, nrow, lane);
@@ -979,17 +995,27 @@ __global__ void __launch_bounds__(CT, 1)
                 tc::tmem_ld8(tl + T_Y + j0, ty);
                 tc::tmem_ld8(tl + T_FB + j0, fb);
                 tc::tmem_wait_ld();
+                const float2 alk2 = make_float2(alk, alk);
+                float2 ep2 = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int j = j0 + e;
-                    const float rinv = tc::rcp_approx(als[e]);
-                    const float ze = (GATE == 2) ? rinv : 1.f;
-                    const float dec = alk * rinv;                  // lambda / gamma_j
-                    const float Yt = ze * ty[e] + fb[e] * dec;     // Y_bar / gamma
-                    dkv[e] += Yt;
-                    gb[e] -= kvs[e] * Yt;
-                    if (j < n) endp = fmaf(kvs[e] * dec, fb[e], endp);   // F_j . F_bar_j
+                for (int e = 0; e < 8; e += 2) {
+                    const float2 rinv2 = make_float2(tc::rcp_approx(als[e]), tc::rcp_approx(als[e + 1]));
+                    const float2 ze2 = (GATE == 2) ? rinv2 : make_float2(1.f, 1.f);
+                    const float2 dec2 = __fmul2_rn(alk2, rinv2);              // lambda / gamma_j
+                    const float2 fb2 = make_float2(fb[e], fb[e + 1]);
+                    const float2 Yt2 = __ffma2_rn(ze2, make_float2(ty[e], ty[e + 1]), __fmul2_rn(fb2, dec2));   // Y_bar / gamma
+                    const float2 nkv2 = make_float2(-kvs[e], -kvs[e + 1]);
+                    const float2 dk2 = __fadd2_rn(make_float2(dkv[e], dkv[e + 1]), Yt2);
+                    const float2 gb2 = __ffma2_rn(nkv2, Yt2, make_float2(gb[e], gb[e + 1]));
+                    // F_j . F_bar_j, tokens past the chunk end left out
+                    const float2 fm = make_float2((j0 + e < n) ? kvs[e] : 0.f, (j0 + e + 1 < n) ? kvs[e + 1] : 0.f);
+                    ep2 = __ffma2_rn(__fmul2_rn(fm, dec2), fb2, ep2);
+                    dkv[e] = dk2.x;
+                    dkv[e + 1] = dk2.y;
+                    gb[e] = gb2.x;
+                    gb[e + 1] = gb2.y;
                 }
+                endp += ep2.x + ep2.y;
             }
             tc::warp_store_t8(stg, dkv, dk + ((size_t)(tok0 + j0) * H + h) * D + 32 * quad, (size_t)H * D, nrow, lane);
             if (GATE == 2) {

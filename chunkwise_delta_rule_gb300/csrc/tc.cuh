@@ -433,6 +433,16 @@ __device__ __forceinline__ float warp_sum8_spread(const float (&v)[8], int lane)
     return a1;
 }
 
+// Four 8 x 8 blocks of 16-bit elements from shared memory, transposed on the way: lanes 8i..8i+7
+// give the row addresses (16 bytes each) of block i; lane t receives, for every block, the elements
+// (rows 2 (t % 4) and 2 (t % 4) + 1, column t / 4) packed low / high.
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
+}
+
 // Approximate reciprocal (the PTX rcp.approx instruction, about 1 ulp); for
 // operands that are rounded to bf16 afterwards.
 __device__ __forceinline__ float rcp_approx(float x) {
