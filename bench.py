@@ -116,6 +116,9 @@ def kernel_work(case, save=False):
     st = 2 * 4 * d * d * case.N   # initial/final state (or its adjoint) per sequence, read + write
     for kname in ("k_fwd_scan_tc", "k_bwd_scan_tc"):
         by[kname] += st
+    # the joint schedule: the reverse scans and the consumer in one launch
+    fl["k_bwd_joint_tc"] = fl["k_bwd_scan_tc"] + fl["k_bwd_consumer_tc"]
+    by["k_bwd_joint_tc"] = by["k_bwd_scan_tc"] + by["k_bwd_consumer_tc"]
     return {k: (fl[k] * case.H, by[k] * case.H) for k in fl}
 
 
@@ -138,6 +141,8 @@ def io_bytes(case):
         "k_bwd_scan_tc": tok * d * e + 2 * st,
         "k_bwd_consumer_tc": tok * (4 * d * e + e + gb + 3 * d * e + e + gb),
     }
+    # the joint schedule: the consumer's inputs and outputs plus the reverse scan's states (dO once)
+    by["k_bwd_joint_tc"] = by["k_bwd_consumer_tc"] + 2 * st
     for k in ("k_prep", "k_fwd_scan", "k_bwd_scan", "k_bwd_dstate", "k_bwd_intra"):
         by.setdefault(k, 0.0)
     by["k_prep"] = by["k_prep_tc"]

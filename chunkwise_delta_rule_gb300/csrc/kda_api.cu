@@ -39,8 +39,9 @@ kda_status check_dims(const kda_problem* p, Dims& d, bool chunked = true) {
         return fail(KDA_ERR_INVALID_ARG, "unknown gate kind");
     if (p->save_policy != 0 && p->save_policy != 1)
         return fail(KDA_ERR_INVALID_ARG, "save_policy must be 0 or 1");
-    if (p->schedule < 0 || p->schedule > kda::MAX_PIECES)
-        return fail(KDA_ERR_INVALID_ARG, "schedule must be 0 (default), 1 (one pass) or a piece count up to 8");
+    if (p->schedule < 0 || (p->schedule > kda::MAX_PIECES && p->schedule != kda::SCHEDULE_JOINT))
+        return fail(KDA_ERR_INVALID_ARG,
+                    "schedule must be 0 (default), 1 (one pass), a piece count up to 8, or 9 (joint)");
     if (p->qk_l2norm != 0 && p->qk_l2norm != 1) return fail(KDA_ERR_INVALID_ARG, "qk_l2norm must be 0 or 1");
     if (p->HV != 0 && p->HV != p->H && (p->HV < p->H || p->HV % p->H != 0 || p->HV > 65535))
         return fail(KDA_ERR_INVALID_ARG, "HV must be 0 or a multiple of H (at most 65535)");
@@ -99,7 +100,7 @@ Layout layout(const Dims& d) {
     L.ftc_b = up(2 * chd * BT * BT) + up(2 * chd * D * D) + up(2 * chd * BT * D);
     L.btc = up(2 * chd * D * D) + up(2 * chd * BT * D);
     L.wscr = up(4 * chd * BT * D) * 3 + up(4 * chd * BT * BT) * 2 + up(4 * chd * D) + up(4 * chd * BT);
-    if (d.per) L.piece = 2 * up(4 * N * H * D * D) + up(4 * kda::MAX_PIECES);
+    if (d.per) L.piece = 2 * up(4 * N * H * D * D) + up(4 * kda::MAX_PIECES) + up(4 * chd);
     return L;
 }
 
@@ -491,14 +492,25 @@ bool scans_fit_together(const kda::Shape& s) { return 2L * s.N * s.H <= (long)kd
 
 // Time pieces of the tensor-core backward (equal-length batches only): the reverse scan runs piece by
 // piece, latest first, and each piece's units are consumed on the side stream while the scan goes on
-// with the next piece, on the SMs it leaves idle. schedule 1 = one pass, P >= 2 = P pieces, 0 = the
-// library's choice: DEFAULT_PIECES when the intermediates are saved and the scan's CTAs fill at most
-// half of the SMs (under recompute the side stream already carries the recomputed scan ahead of the
-// consumers, and one pass measured faster). At least two chunks per piece.
+// with the next piece, on the SMs it leaves idle. schedule 1 = one pass, P >= 2 = P pieces; the
+// library's choice is the joint schedule where it applies and one pass elsewhere (under recompute
+// the side stream already carries the recomputed scan ahead of the consumers, and one pass measured
+// faster than pieces). At least two chunks per piece.
+// The joint schedule: equal-length batches under the save policy whose scans fit beside the
+// consumer (one (sequence, head) pair per SM at most). Asked for with schedule 9; the library's
+// choice (schedule 0) when the scans leave at least half of the SMs to the consumer (measured:
+// backward 0.855 ms against 0.950 in three pieces and 1.026 in one pass at the KDA workload, 0.408
+// against 0.445 / 0.459 at the DeltaNet one; with 128 pairs on 152 SMs one pass was faster, 0.939
+// against 0.971).
+bool bwd_joint(const kda_problem* p, const Dims& d) {
+    if (!d.per || !p->save_policy) return false;
+    const long pairs = (long)d.N * d.H, sms = kda::sm_count();
+    return p->schedule == kda::SCHEDULE_JOINT ? pairs <= sms : (p->schedule == 0 && 2 * pairs <= sms);
+}
+
 int bwd_pieces(const kda_problem* p, const Dims& d) {
-    if (!d.per) return 1;
-    int P = p->schedule >= 2 ? p->schedule : p->schedule == 1 ? 1
-            : (p->save_policy && 2L * d.N * d.H <= (long)kda::sm_count() ? kda::DEFAULT_PIECES : 1);
+    if (!d.per || p->schedule == kda::SCHEDULE_JOINT) return 1;
+    int P = p->schedule >= 2 ? p->schedule : 1;
     while (P > 1 && d.per < 2 * P) --P;
     return P;
 }
@@ -697,6 +709,26 @@ static kda_status chunk_bwd_core(const kda_problem* p, const void* dout, const f
             }
             e = traced("k_fwd_scan_tc_recompute", rs, [&] { return kda::launch_fwd_scan_tc(s, 2, p->h0, t, f, nullptr, nullptr, rs); });
             if (e != cudaSuccess) return cuda_fail(e, "forward scan (recompute)");
+        }
+        if (bwd_joint(p, d)) {
+            // the joint schedule: scans and consumer in one cooperative launch; the ready flags and the
+            // unit counter start at zero
+            cw.take<float>(state_bytes(d));
+            cw.take<float>(state_bytes(d));
+            int* ctr = cw.take<int>(4 * kda::MAX_PIECES);
+            int* flags = cw.take<int>(sizeof(int) * (size_t)d.NC * d.H);
+            if ((e = cudaMemsetAsync(ctr, 0, 4 * kda::MAX_PIECES, cs)) != cudaSuccess ||
+                (e = cudaMemsetAsync(flags, 0, sizeof(int) * (size_t)d.NC * d.H, cs)) != cudaSuccess)
+                return cuda_fail(e, "joint schedule flags");
+            kda::ConsPiece pc;
+            pc.per = d.per;
+            pc.ctr = ctr;
+            pc.flags = flags;
+            e = traced("k_bwd_joint_tc", cs, [&] { return kda::launch_bwd_joint_tc(s, gate, p->q, p->k, p->v, p->beta, p->g, dout, dht, dh0, t, f, b, dq, dk, dv, dbeta, dg, cs, gd, pc); });
+            if (e != cudaSuccess) return cuda_fail(e, "joint scan and consumer");
+            e = traced("k_bwd_wide", cs, [&] { return gate == KDA_GATE_NONE ? cudaSuccess : kda::launch_bwd_wide(s, gate, p->q, p->k, p->v, p->beta, p->g, dout, t, f, b, scr, dq, dk, dv, dbeta, dg, cs, gd); });
+            if (e != cudaSuccess) return cuda_fail(e, "consumer (wide chunks)");
+            return KDA_OK;
         }
         int P = bwd_pieces(p, d);
         if (P > 1 && !sd) {

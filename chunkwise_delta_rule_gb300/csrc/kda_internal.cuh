@@ -271,13 +271,22 @@ cudaError_t launch_fwd_scan_tc(const Shape& s, int mode, const float* h0, Table 
 // piece per launch, latest first, handing the state adjoint on through dht / dh0; the consumer of a
 // piece claims its units from ctr (zeroed before the launch; NULL: a fixed stride per CTA).
 constexpr int MAX_PIECES = 8;       // time pieces of the tensor-core backward, at most
-constexpr int DEFAULT_PIECES = 3;   // the library's choice when the reverse scan leaves SMs idle (measured)
+// The joint schedule (flags set): every unit in one launch, latest chunk first, each waiting for the
+// ready flag of its (chunk slot, head) that the reverse scan sets; ctr hands out the unit indices.
 struct ConsPiece {
     int lo = 0, L = 0, per = 0;
     int* ctr = nullptr;
+    int* flags = nullptr;
 };
+constexpr int SCHEDULE_JOINT = 9;   // kda_problem.schedule value of the joint schedule
 cudaError_t launch_bwd_scan_tc(const Shape& s, const void* dout, const float* dht, Table t, FwdTC f,
                                BwdTC b, float* dh0, cudaStream_t st, const ConsPiece& pc = ConsPiece{});
+// The joint schedule: reverse scans and consumer in one cooperative launch of one CTA per SM
+// (N * H at most the SM count; pc.per, pc.ctr and pc.flags set, ctr and flags zeroed before the launch).
+cudaError_t launch_bwd_joint_tc(const Shape& s, int gate, const void* q, const void* k, const void* v,
+                                const void* beta, const float* g, const void* dout, const float* dht, float* dh0,
+                                Table t, FwdTC f, BwdTC b, void* dq, void* dk, void* dv, void* dbeta, float* dg,
+                                cudaStream_t st, const Gdn2& gd, const ConsPiece& pc);
 cudaError_t launch_bwd_consumer_tc(const Shape& s, int gate, const void* q, const void* k, const void* v,
                                    const void* beta, const float* g, const void* dout, Table t, FwdTC f,
                                    BwdTC b, void* dq, void* dk, void* dv, void* dbeta, float* dg,

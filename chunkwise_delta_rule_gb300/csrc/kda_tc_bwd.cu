@@ -97,7 +97,7 @@ __device__ __forceinline__ void bscan_fill(uint32_t stg, const FwdTC& f, size_t 
 __device__ __forceinline__ void bscan_compute(const Shape& s, const float* __restrict__ dht, const Table& t,
                                               const FwdTC& f, const BwdTC& b, float* __restrict__ dh0,
                                               unsigned char* base, uint64_t* bar, uint32_t tb, int nseq, int h,
-                                              int c0, int c1) {
+                                              int c0, int c1, const int* flags) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = warp & 3, half = warp >> 2;
     float* sLam = reinterpret_cast<float*>(base + B_LAM);
@@ -236,6 +236,7 @@ __device__ __forceinline__ void bscan_compute(const Shape& s, const float* __res
         wait_one(&bar[1], last & 1);
         wait_one(&bar[2 + (last & 1)], (last >> 1) & 1);
         store_p(c0, last & 1);
+        if (flags) __threadfence();   // P of the first chunk, published after the CTA barrier
     }
     if (ok && dh0) {
 #pragma unroll 1
@@ -253,7 +254,7 @@ __device__ __forceinline__ void bscan_compute(const Shape& s, const float* __res
 // chunk (warp-uniform descriptors, one elected lane issuing).
 __device__ __forceinline__ void bscan_issue(const Shape& s, const Table& t, const FwdTC& f, const BwdTC& b,
                                             const CUtensorMap* tmo, uint32_t sb, uint64_t* bar, uint64_t* full,
-                                            uint32_t tb, int h, int c0, int c1, int& filled, int& waited) {
+                                            uint32_t tb, int h, int c0, int c1, int& filled, int& waited, int* flags) {
     const int lane = threadIdx.x & 31;
     const int H = s.H;
     const uint32_t i64 = tc::idesc_bf16(128, 64), m64 = tc::idesc_bf16_bmn(128, 64),
@@ -295,6 +296,12 @@ __device__ __forceinline__ void bscan_issue(const Shape& s, const Table& t, cons
                 if (it >= 2) tc::bulk_s2g(b.P + ((size_t)(c + 2) * H + h) * BT * D, sb + B_PST, BT * D * 2);
                 tc::bulk_commit();
                 tc::bulk_wait_read();
+                // joint schedule: the group committed one iteration ago (S+bar of chunk c+2, P of chunk
+                // c+3) is complete, so chunk c+3 (whose S+bar went out an iteration before) is ready
+                if (flags && it >= 3) {
+                    tc::bulk_wait_prev();
+                    tc::publish_flag(flags + (size_t)(c + 3) * H + h);
+                }
             }
         }
         __syncwarp();
@@ -317,19 +324,19 @@ __device__ __forceinline__ void bscan_issue(const Shape& s, const Table& t, cons
     }
 }
 
-__global__ void __launch_bounds__(ST_ALL, 1)
-    k_bwd_scan_tc(Shape s, const __grid_constant__ CUtensorMap tmo, const float* __restrict__ dht, Table t,
-                  FwdTC f, BwdTC b, float* __restrict__ dh0, int plo, int pl) {
-    extern __shared__ unsigned char smem_raw[];
-    unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                           ~static_cast<uintptr_t>(1023));
+// The reverse scan of one (sequence, head), or of one time piece of it (chunks plo .. plo+pl-1: dht is
+// then the state adjoint leaving the piece and dh0 the one entering it), by a CTA of ST_ALL or more
+// threads: warps 0..7 compute, warp 8 issues, further warps only meet the CTA barriers. tb: 512 TMEM
+// columns allocated by the caller. flags (the joint schedule): a ready flag per (chunk slot, head), set
+// once the chunk's S+bar and P are in HBM.
+__device__ __forceinline__ void bscan_body(const Shape& s, const CUtensorMap* tmo, const float* __restrict__ dht,
+                                           const Table& t, const FwdTC& f, const BwdTC& b, float* __restrict__ dh0,
+                                           int nseq, int h, int plo, int pl, int* flags, unsigned char* base,
+                                           uint32_t tb) {
     uint64_t* bar = reinterpret_cast<uint64_t*>(base + B_BAR);   // R_bar, state adjoint update, P (x2)
     uint64_t* full = bar + 4;                                      // operand stages 0, 1
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 6);
     const uint32_t sb = tc::smem_u32(base);
-    const int nseq = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5;
-    // the sequence's chunks, or those of one time piece (chunks plo .. plo+pl-1 of it): dht is then
-    // the state adjoint leaving the piece and dh0 the one entering it
+    const int tid = threadIdx.x, warp = tid >> 5;
     const int c0 = t.seq_chunk0[nseq] + (pl ? plo : 0), c1 = pl ? c0 + pl : t.seq_chunk0[nseq + 1];
     const bool issuer = warp == ST / 32;
     int filled = 0, waited = 0;   // bulk fills issued / consumed (issuer lane 0)
@@ -338,11 +345,42 @@ __global__ void __launch_bounds__(ST_ALL, 1)
         for (int i = 0; i < 6; ++i) tc::mbar_init(&bar[i], 1);
         tc::fence_mbar_init();
         if (c0 < c1) {
-            bscan_fill(sb + B_STAGE, f, (size_t)(c1 - 1) * s.H + h, &tmo, h, t.chunk_tok0[c1 - 1], &full[0]);
+            bscan_fill(sb + B_STAGE, f, (size_t)(c1 - 1) * s.H + h, tmo, h, t.chunk_tok0[c1 - 1], &full[0]);
             filled = 1;
         }
     }
-    if (warp == 0) {
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (issuer)
+        bscan_issue(s, t, f, b, tmo, sb, bar, full, tb, h, c0, c1, filled, waited, flags);
+    else if (warp < ST / 32)
+        bscan_compute(s, dht, t, f, b, dh0, base, bar, tb, nseq, h, c0, c1, flags);
+    // a bulk fill still in flight (only after a timeout) lands before the CTA moves on
+    if (issuer && (tid & 31) == 0)
+        for (; waited < filled; ++waited) tc::mbar_wait(&full[waited & 1], (waited >> 1) & 1);
+    tc::fence_before_sync();
+    __syncthreads();
+    // S+bar of the first chunk and P of the one after it, staged in the last iteration; the chunks not
+    // published inside the loop are published now
+    if (issuer && (tid & 31) == 0 && c1 > c0) {
+        tc::bulk_s2g(b.SBP + ((size_t)c0 * s.H + h) * D * D, sb + B_SST, D * D * 2);
+        if (c1 - c0 >= 2) tc::bulk_s2g(b.P + ((size_t)(c0 + 1) * s.H + h) * BT * D, sb + B_PST, BT * D * 2);
+        tc::bulk_commit();
+        tc::bulk_wait_all();
+        if (flags)
+            for (int c = c0; c < c1 && c < c0 + 3; ++c) tc::publish_flag(flags + (size_t)c * s.H + h);
+    }
+}
+
+__global__ void __launch_bounds__(ST_ALL, 1)
+    k_bwd_scan_tc(Shape s, const __grid_constant__ CUtensorMap tmo, const float* __restrict__ dht, Table t,
+                  FwdTC f, BwdTC b, float* __restrict__ dh0, int plo, int pl) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                           ~static_cast<uintptr_t>(1023));
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(base + B_BAR + 48);
+    if (threadIdx.x < 32) {
         tc::tmem_alloc(tslot, 512);
         tc::tmem_relinquish();
     }
@@ -350,23 +388,10 @@ __global__ void __launch_bounds__(ST_ALL, 1)
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tb = *tslot;
-    if (issuer)
-        bscan_issue(s, t, f, b, &tmo, sb, bar, full, tb, h, c0, c1, filled, waited);
-    else
-        bscan_compute(s, dht, t, f, b, dh0, base, bar, tb, nseq, h, c0, c1);
-    // a bulk fill still in flight (only after a timeout) lands before the CTA leaves
-    if (issuer && (tid & 31) == 0)
-        for (; waited < filled; ++waited) tc::mbar_wait(&full[waited & 1], (waited >> 1) & 1);
+    bscan_body(s, &tmo, dht, t, f, b, dh0, blockIdx.x, blockIdx.y, plo, pl, nullptr, base, tb);
     tc::fence_before_sync();
     __syncthreads();
-    // S+bar of the first chunk and P of the one after it, staged in the last iteration
-    if (issuer && (tid & 31) == 0 && c1 > c0) {
-        tc::bulk_s2g(b.SBP + ((size_t)c0 * s.H + h) * D * D, sb + B_SST, D * D * 2);
-        if (c1 - c0 >= 2) tc::bulk_s2g(b.P + ((size_t)(c0 + 1) * s.H + h) * BT * D, sb + B_PST, BT * D * 2);
-        tc::bulk_commit();
-        tc::bulk_wait_all();
-    }
-    if (warp == 0) tc::tmem_dealloc(tb, 512);
+    if (threadIdx.x < 32) tc::tmem_dealloc(tb, 512);
 }
 
 // ================================================== k_bwd_consumer_tc
@@ -409,6 +434,10 @@ static_assert(X_SCR + 12 * D * 4 <= C_A && X_STG + 16 * 512 <= C_A, "staging reg
 static_assert(X_OP % 1024 == 0 && X_V % 1024 == 0 && X_SB % 1024 == 0 && X_DH % 1024 == 0 && X_BT % 1024 == 0 &&
               C_A % 1024 == 0 && C_K % 1024 == 0 && C_Q % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 static_assert(CONS_SMEM <= 232448, "consumer shared memory above the per-block limit");
+// The joint kernel: the larger of the two maps; its TMEM slot lies past both roles' barriers.
+constexpr int J_SLOT = B_BAR + 56;
+constexpr int JOINT_SMEM = BSCAN_SMEM > CONS_SMEM ? BSCAN_SMEM : CONS_SMEM;
+static_assert(J_SLOT + 4 <= JOINT_SMEM - 1024 && C_BAR + 40 <= J_SLOT, "joint kernel TMEM slot");
 
 __device__ __forceinline__ float bfx(const bf16* p) { return __bfloat162float(*p); }
 
@@ -451,25 +480,33 @@ __device__ __forceinline__ float bf_lo_hi(uint32_t w, int hi) { return __uint_as
 // a batch of equal-length sequences of `per` chunks each, chunks lo .. lo+L-1 of every sequence
 // (i runs over sequence, then chunk, then head). A CTA takes index blockIdx.x first; later indices
 // come from the launch's counter (zeroed before the launch) or, without one, in strides of gridDim.
+// The joint schedule (pc.flags set) runs every unit, latest chunk first (the order in which the
+// reverse scans finish them): index i is chunk per-1-i/(N H) of sequence (i mod N H) / H, head i mod H;
+// every index comes from the launch's counter.
 __device__ __forceinline__ int piece_units(const ConsPiece& pc, int N, int H, int total) {
-    return pc.L ? N * pc.L * H : total;
+    return pc.flags ? total : pc.L ? N * pc.L * H : total;
 }
-__device__ __forceinline__ int piece_unit(const ConsPiece& pc, int i, int H) {
+__device__ __forceinline__ int piece_unit(const ConsPiece& pc, int i, int N, int H) {
+    if (pc.flags) {
+        const int NH = N * H, r = i / NH, p = i - r * NH;
+        return ((p / H) * pc.per + pc.per - 1 - r) * H + p % H;
+    }
     if (!pc.L) return i;
     const int LH = pc.L * H, n = i / LH, r = i - n * LH;
     return (n * pc.per + pc.lo + r / H) * H + r % H;
 }
 __device__ __forceinline__ int claim_next(const ConsPiece& pc, int i) {
+    if (pc.flags) return atomicAdd(pc.ctr, 1);
     return pc.ctr ? (int)gridDim.x + atomicAdd(pc.ctr, 1) : i + (int)gridDim.x;
 }
 
 // The first unit at index i or after it (claiming further indices) that has tokens and a narrow
 // gate range (-1 when none is left); i ends at that unit's index, n and tok0 give its chunk extent.
 template <int GATE>
-__device__ __forceinline__ int cons_find(int& i, int units, const ConsPiece& pc, int H, const Table& t,
+__device__ __forceinline__ int cons_find(int& i, int units, const ConsPiece& pc, int N, int H, const Table& t,
                                          const FwdTC& f, int& n, int& tok0) {
     for (; i < units; i = claim_next(pc, i)) {
-        const int u = piece_unit(pc, i, H), c = u / H;
+        const int u = piece_unit(pc, i, N, H), c = u / H;
         n = t.chunk_len[c];
         if (n > 0 && (GATE == 0 || f.WIDE[u] == 0)) {
             tok0 = t.chunk_tok0[c];
@@ -532,17 +569,18 @@ __device__ __forceinline__ bool cons_wait(uint64_t* b, int& w, int32_t* err) {
     return ok;
 }
 
+// The consumer loop of one CTA (CT threads): units from the launch's index space until none is left.
+// tb: 512 TMEM columns allocated by the caller. In the joint schedule the X tiles of a unit are loaded
+// once its ready flag is set.
 template <int GATE, bool GD2>
-__global__ void __launch_bounds__(CT, 1)
-    k_bwd_consumer_tc(Shape s, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                      const __grid_constant__ CUtensorMap tmo, const __grid_constant__ CUtensorMap tmg,
-                      const __grid_constant__ CUtensorMap tmv, const bf16* __restrict__ beta,
-                      const float* __restrict__ g, Table t, FwdTC f, BwdTC bw, bf16* __restrict__ dq,
-                      bf16* __restrict__ dk, bf16* __restrict__ dv, bf16* __restrict__ dbeta,
-                      float* __restrict__ dg, Gdn2 gd, ConsPiece pc) {
-    extern __shared__ unsigned char smem_raw[];
-    unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                           ~static_cast<uintptr_t>(1023));
+__device__ __forceinline__ void cons_body(const Shape& s, const CUtensorMap* tmq_, const CUtensorMap* tmk_,
+                                          const CUtensorMap* tmo_, const CUtensorMap* tmg_, const CUtensorMap* tmv_,
+                                          const bf16* __restrict__ beta, const float* __restrict__ g, const Table& t,
+                                          const FwdTC& f, const BwdTC& bw, bf16* __restrict__ dq,
+                                          bf16* __restrict__ dk, bf16* __restrict__ dv, bf16* __restrict__ dbeta,
+                                          float* __restrict__ dg, const Gdn2& gd, const ConsPiece& pc,
+                                          unsigned char* base, uint32_t tb) {
+    const CUtensorMap &tmq = *tmq_, &tmk = *tmk_, &tmo = *tmo_, &tmg = *tmg_, &tmv = *tmv_;
     float* sA = reinterpret_cast<float*>(base + C_A);
     const unsigned char* sK = base + C_K;
     const unsigned char* sQ = base + C_Q;
@@ -564,7 +602,6 @@ __global__ void __launch_bounds__(CT, 1)
     uint64_t* bldC = bar + 1;                                     // load groups C, X1, X2
     uint64_t* bldX1 = bar + 2;
     uint64_t* bldX2 = bar + 3;
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 4);
     const uint32_t sb = tc::smem_u32(base);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -572,6 +609,7 @@ __global__ void __launch_bounds__(CT, 1)
     const int H = s.H, units = piece_units(pc, s.N, s.H, s.NC * s.H);
     const float scale = s.scale;
     int icur = (int)blockIdx.x, icand = units;   // indices of the current unit and the candidate (thread LDR)
+    const int N = s.N;
     int nC = 0, nX1 = 0, nX2 = 0;   // load groups issued (thread LDR)
     int wC = 0, wX1 = 0, wX2 = 0;   // load groups waited for (every thread)
     // this thread's key (TMEM lane) and token group in the key-major passes, and the key's byte
@@ -584,27 +622,24 @@ __global__ void __launch_bounds__(CT, 1)
     if (tid == LDR) {
         for (int i = 0; i < 4; ++i) tc::mbar_init(&bar[i], 1);
         tc::fence_mbar_init();
+        if (pc.flags) icur = atomicAdd(pc.ctr, 1);
         int n0 = 0, t0 = 0;
-        const int u0 = cons_find<GATE>(icur, units, pc, H, t, f, n0, t0);
+        const int u0 = cons_find<GATE>(icur, units, pc, N, H, t, f, n0, t0);
         sMeta[0] = u0;
         sMeta[1] = n0;
         sMeta[2] = t0;
         if (u0 >= 0) {
             const int h0 = u0 % H;
             cons_load_c<GATE>(sb, &tmk, &tmq, &tmg, h0, t0, bldC);
+            if (pc.flags && !tc::wait_flag(pc.flags + u0, t.err)) atomicOr(t.err, 2);
             cons_load_x1(sb, f, bw, (size_t)u0, bldX1);
             cons_load_x2(sb, &tmo, &tmv, bw, (size_t)u0, h0, t0, bldX2);
             nC = nX1 = nX2 = 1;
         }
     }
-    if (warp == 0) {
-        tc::tmem_alloc(tslot, 512);
-        tc::tmem_relinquish();
-    }
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    const uint32_t tb = *tslot;
     const uint32_t tl = tc::taddr(tb, 32 * quad, 0);
     bf16 beta_nx = __float2bfloat16_rn(0.f);   // beta of the next unit (threads < BT), read during this one
     int cand = 0, cn = 0, ct0 = 0, cw = 0;   // next-unit candidate and its table entries (thread LDR)
@@ -619,7 +654,7 @@ __global__ void __launch_bounds__(CT, 1)
         if (tid == LDR) {   // the next candidate and its table entries
             icand = claim_next(pc, icur);
             if (icand < units) {
-                cand = piece_unit(pc, icand, H);
+                cand = piece_unit(pc, icand, N, H);
                 cn = __ldg(t.chunk_len + cand / H);
                 ct0 = __ldg(t.chunk_tok0 + cand / H);
                 cw = (GATE != 0) ? __ldg(f.WIDE + cand) : 0;
@@ -679,7 +714,7 @@ __global__ void __launch_bounds__(CT, 1)
                 icur = icand;
             } else if (icand < units) {
                 icur = claim_next(pc, icand);
-                nxt = cons_find<GATE>(icur, units, pc, H, t, f, nn, nt);
+                nxt = cons_find<GATE>(icur, units, pc, N, H, t, f, nn, nt);
             }
             int* wm = sMeta + 4 * ((k + 1) & 1);
             wm[0] = nxt;
@@ -909,6 +944,7 @@ __global__ void __launch_bounds__(CT, 1)
         tc::fence_after_sync();
         // groups X1 and X2 of the next unit into the X region, free since the phase-B MMAs completed
         if (tid == LDR && nm[0] >= 0) {
+            if (pc.flags && !tc::wait_flag(pc.flags + nm[0], t.err)) atomicOr(t.err, 2);
             cons_load_x1(sb, f, bw, (size_t)nm[0], bldX1);
             cons_load_x2(sb, &tmo, &tmv, bw, (size_t)nm[0], nm[0] % H, nm[2], bldX2);
             ++nX1;
@@ -1085,9 +1121,70 @@ __global__ void __launch_bounds__(CT, 1)
         for (; wX1 < nX1; ++wX1) tc::mbar_wait(bldX1, wX1 & 1);
         for (; wX2 < nX2; ++wX2) tc::mbar_wait(bldX2, wX2 & 1);
     }
+}
+
+template <int GATE, bool GD2>
+__global__ void __launch_bounds__(CT, 1)
+    k_bwd_consumer_tc(Shape s, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                      const __grid_constant__ CUtensorMap tmo, const __grid_constant__ CUtensorMap tmg,
+                      const __grid_constant__ CUtensorMap tmv, const bf16* __restrict__ beta,
+                      const float* __restrict__ g, Table t, FwdTC f, BwdTC bw, bf16* __restrict__ dq,
+                      bf16* __restrict__ dk, bf16* __restrict__ dv, bf16* __restrict__ dbeta,
+                      float* __restrict__ dg, Gdn2 gd, ConsPiece pc) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                           ~static_cast<uintptr_t>(1023));
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(base + C_BAR + 32);
+    if (threadIdx.x < 32) {
+        tc::tmem_alloc(tslot, 512);
+        tc::tmem_relinquish();
+    }
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 0) tc::tmem_dealloc(tb, 512);
+    tc::fence_after_sync();
+    const uint32_t tb = *tslot;
+    cons_body<GATE, GD2>(s, &tmq, &tmk, &tmo, &tmg, &tmv, beta, g, t, f, bw, dq, dk, dv, dbeta, dg, gd, pc, base, tb);
+    tc::fence_before_sync();
+    __syncthreads();
+    if (threadIdx.x < 32) tc::tmem_dealloc(tb, 512);
+}
+
+// The joint schedule in one cooperative launch of one CTA per SM: CTA n H + h (n < N) first runs the
+// reverse scan of sequence n, head h, publishing each chunk as its S+bar and P reach HBM, then joins
+// the other CTAs in the consumer loop, which takes the units latest chunk first and waits for each
+// unit's flag before loading its scan outputs. No CTA waits for one that is not running: the launch
+// is cooperative, so all of them are resident, and the scans never wait for the consumers.
+template <int GATE, bool GD2>
+__global__ void __launch_bounds__(CT, 1)
+    k_bwd_joint_tc(Shape s, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                   const __grid_constant__ CUtensorMap tmo, const __grid_constant__ CUtensorMap tmg,
+                   const __grid_constant__ CUtensorMap tmv, const float* __restrict__ dht, float* __restrict__ dh0,
+                   const bf16* __restrict__ beta, const float* __restrict__ g, Table t, FwdTC f, BwdTC bw,
+                   bf16* __restrict__ dq, bf16* __restrict__ dk, bf16* __restrict__ dv, bf16* __restrict__ dbeta,
+                   float* __restrict__ dg, Gdn2 gd, ConsPiece pc) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                           ~static_cast<uintptr_t>(1023));
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(base + J_SLOT);
+    if (threadIdx.x < 32) {
+        tc::tmem_alloc(tslot, 512);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tb = *tslot;
+    if ((int)blockIdx.x < s.N * s.H) {
+        bscan_body(s, &tmo, dht, t, f, bw, dh0, (int)blockIdx.x / s.H, (int)blockIdx.x % s.H, 0, 0, pc.flags, base, tb);
+        tc::fence_async_smem();   // the scan's shared-memory writes before the consumer's tile loads land
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+    }
+    cons_body<GATE, GD2>(s, &tmq, &tmk, &tmo, &tmg, &tmv, beta, g, t, f, bw, dq, dk, dv, dbeta, dg, gd, pc, base, tb);
+    tc::fence_before_sync();
+    __syncthreads();
+    if (threadIdx.x < 32) tc::tmem_dealloc(tb, 512);
 }
 
 template <int GATE, bool GD2>
@@ -1111,7 +1208,48 @@ cudaError_t run_consumer(const Shape& s, const void* q, const void* k, const voi
     return cudaGetLastError();
 }
 
+template <int GATE, bool GD2>
+cudaError_t run_joint(const Shape& s, const void* q, const void* k, const void* v, const void* beta, const float* g,
+                      const void* dout, const float* dht, float* dh0, Table t, FwdTC f, BwdTC b, void* dq, void* dk,
+                      void* dv, void* dbeta, float* dg, cudaStream_t st, const Gdn2& gd, const ConsPiece& pc) {
+    cudaError_t e = set_smem_once<k_bwd_joint_tc<GATE, GD2>>(JOINT_SMEM);
+    if (e != cudaSuccess) return e;
+    CUtensorMap mq, mk, mo, mg, mv;
+    memset(&mg, 0, sizeof(mg));
+    if (!tmap_rows_bf16(&mq, q, s.Ttot, s.H, D) || !tmap_rows_bf16(&mk, k, s.Ttot, s.H, D) ||
+        !tmap_rows_bf16(&mo, dout, s.Ttot, s.H, D) || !tmap_rows_bf16(&mv, v, s.Ttot, s.H, D) ||
+        (GATE == 2 && !tmap_rows_f32(&mg, g, s.Ttot, s.H, D)))
+        return cudaErrorInvalidValue;
+    const int grid = sm_count();
+    if (s.N * s.H > grid || !pc.flags || !pc.ctr) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(CT);
+    cfg.dynamicSmemBytes = JOINT_SMEM;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;   // every CTA resident: consumers may wait for scan CTAs
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_bwd_joint_tc<GATE, GD2>, s, mq, mk, mo, mg, mv, dht, dh0, (const bf16*)beta, g,
+                              t, f, b, (bf16*)dq, (bf16*)dk, (bf16*)dv, (bf16*)dbeta, dg, gd, pc);
+}
+
 }  // namespace
+
+cudaError_t launch_bwd_joint_tc(const Shape& s, int gate, const void* q, const void* k, const void* v,
+                                const void* beta, const float* g, const void* dout, const float* dht, float* dh0,
+                                Table t, FwdTC f, BwdTC b, void* dq, void* dk, void* dv, void* dbeta, float* dg,
+                                cudaStream_t st, const Gdn2& gd, const ConsPiece& pc) {
+#define KDA_JOINT(G, X) run_joint<G, X>(s, q, k, v, beta, g, dout, dht, dh0, t, f, b, dq, dk, dv, dbeta, dg, st, gd, pc)
+    switch (gate) {
+        case 0: return gd.erase ? KDA_JOINT(0, true) : KDA_JOINT(0, false);
+        case 1: return gd.erase ? KDA_JOINT(1, true) : KDA_JOINT(1, false);
+        default: return gd.erase ? KDA_JOINT(2, true) : KDA_JOINT(2, false);
+    }
+#undef KDA_JOINT
+}
 
 cudaError_t launch_bwd_scan_tc(const Shape& s, const void* dout, const float* dht, Table t, FwdTC f, BwdTC b,
                                float* dh0, cudaStream_t st, const ConsPiece& pc) {

@@ -170,6 +170,40 @@ __device__ __forceinline__ void bulk_wait_read_prev() {
     asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// The writes of all but the most recent group are complete.
+__device__ __forceinline__ void bulk_wait_prev() { asm volatile("cp.async.bulk.wait_group 1;" ::: "memory"); }
+
+// Cross-SM hand-off of data written to global memory. publish: after the writes are complete
+// (bulk copies: waited for; generic stores: this thread's, or the CTA's after a barrier), orders
+// them before a release store of 1 to the flag. ready: an acquire load of the flag; once it reads
+// nonzero, bulk copies issued afterwards see the published data.
+__device__ __forceinline__ void publish_flag(int* flag) {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    __threadfence();
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(flag), "r"(1) : "memory");
+}
+__device__ __forceinline__ bool flag_set(const int* flag) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+    return v != 0;
+}
+// Waits (about 1 s at most) for a published flag; false if it never came, or at once if the error
+// word err already records a wait that gave up (so that one lost flag costs one second, not one per
+// waiting unit). The caller records a failure in err.
+__device__ __forceinline__ bool wait_flag(const int* flag, const int32_t* err) {
+    if (!flag_set(flag)) {
+        const uint64_t t0 = global_ns();
+        for (uint32_t i = 1;; ++i) {
+            if (flag_set(flag)) break;
+            if ((i & 63u) == 0 &&
+                (global_ns() - t0 > 1000000000ull || (*reinterpret_cast<const volatile int32_t*>(err) & 2)))
+                return false;
+            __nanosleep(64);
+        }
+    }
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    return true;
+}
 
 // Named CTA barrier (id 1..15; 0 is __syncthreads): waits for `count` threads
 // (a multiple of 32).
@@ -431,16 +465,6 @@ __device__ __forceinline__ float warp_sum8_spread(const float (&v)[8], int lane)
     a1 += __shfl_xor_sync(0xffffffffu, a1, 2);
     a1 += __shfl_xor_sync(0xffffffffu, a1, 1);
     return a1;
-}
-
-// Four 8 x 8 blocks of 16-bit elements from shared memory, transposed on the way: lanes 8i..8i+7
-// give the row addresses (16 bytes each) of block i; lane t receives, for every block, the elements
-// (rows 2 (t % 4) and 2 (t % 4) + 1, column t / 4) packed low / high.
-__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr)
-                 : "memory");
 }
 
 // Approximate reciprocal (the PTX rcp.approx instruction, about 1 ulp); for

@@ -101,11 +101,17 @@ typedef struct {
     int save_policy;            /* 0: backward recomputes the forward (policy R);
                                    1: forward fills `saved` for the backward (policy A) */
     int schedule;               /* backward schedule of the tensor-core path for equal-length
-                                   batches: 0 = the library's choice; 1 = one reverse-scan pass,
+                                   batches: 0 = the library's choice (joint under the save policy
+                                   when the pairs fill at most half of the SMs, else one pass);
+                                   1 = one reverse-scan pass,
                                    then the consumer; P = 2..8 = P time pieces, the reverse scan
                                    of piece q+1 running beside the consumer of piece q (on a
-                                   library-owned second stream). Results are identical bitwise
-                                   for every value; other paths ignore it. */
+                                   library-owned second stream); 9 = joint: one cooperative
+                                   launch in which the reverse scans run beside the consumer,
+                                   which takes each chunk as soon as the scan has written its
+                                   state adjoint and sensitivity (save policy, at most one
+                                   (sequence, head) pair per SM; else one pass). Results are
+                                   identical bitwise for every value; other paths ignore it. */
     /* Optional prologue inside the operator ("GatedDeltaNet-2 (NVlabs) — official spec
      * transcription", §2.0, §3, §4.2); all zero / NULL turns it off. */
     const float *A_log;         /* [H] fp32 or NULL. Non-NULL (needs a gate): g holds the raw gate and

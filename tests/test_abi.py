@@ -71,8 +71,9 @@ def test_workspace_size_arithmetic():
     ftc_b = up(2 * chd * BT * BT) + up(2 * chd * D * D) + up(2 * chd * BT * D)
     btc = up(2 * chd * D * D) + up(2 * chd * BT * D)
     wscr = up(4 * chd * BT * D) * 3 + up(4 * chd * BT * BT) * 2 + up(4 * chd * D) + up(4 * chd * BT)
-    # equal-length batches: two fp32 state adjoints and eight claim counters for a backward in time pieces
-    piece = 2 * up(4 * 2 * H * D * D) + up(4 * 8)
+    # equal-length batches: two fp32 state adjoints and eight claim counters for a backward in time
+    # pieces, and a ready flag per chunk x head for the joint schedule
+    piece = 2 * up(4 * 2 * H * D * D) + up(4 * 8) + up(4 * chd)
     assert _ws(ptc, 1) == table + ftc + ftc_b + btc + wscr + piece
     ptca = _prob(io=0, save=1)
     assert _ws(ptca, 0) == table
@@ -99,7 +100,7 @@ def test_workspace_size_arithmetic():
     (dict(io=5), 1),
     (dict(B=2, cu=0x2000, N=3), 1),
     (dict(save=3), 1),
-    (dict(schedule=9), 1),
+    (dict(schedule=10), 1),
     (dict(schedule=-1), 1),
 ])
 def test_invalid_problems_are_rejected_before_launch(kw, status):

@@ -164,12 +164,14 @@ def test_policies_agree_and_runs_are_deterministic(io, D, H):
 
 @pytest.mark.parametrize("gate,policy", [("channel", 1), ("scalar", 0), ("none", 1)])
 def test_backward_schedules_agree_bitwise(gate, policy):
-    """One reverse-scan pass and 2, 3 or 4 time pieces (the scan of a piece running beside the consumer
-    of the one before, the state adjoint handed on in fp32) give bitwise identical results, which match
-    the oracle. 10 chunks per sequence, the last one ragged."""
+    """One reverse-scan pass, 2, 3 or 4 time pieces (the scan of a piece running beside the consumer of
+    the one before, the state adjoint handed on in fp32) and the joint schedule (scans and consumer in
+    one launch, the consumer waiting for each chunk's ready flag; one pass under the recompute policy)
+    give bitwise identical results, which match the oracle. 10 chunks per sequence, the last one
+    ragged."""
     case = make_case(io="bf16", gate=gate, B=2, T=610, H=3, K=128, V=128, seed=44)
     ref = gpu_run(case, policy=policy, schedule=1)
-    for sch in (0, 2, 3, 4):
+    for sch in (0, 2, 3, 4, 9):
         r = gpu_run(case, policy=policy, schedule=sch)
         for name in NAMES:
             if ref[name] is not None:
