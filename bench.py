@@ -561,6 +561,56 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_compare(args):
+    """Schedules of the backward compared in one process, ABBA order: for each listed schedule the
+    forward (save policy) runs once, then rounds of timed backward calls alternate A B B A ..., L2
+    flushed before each call; prints one JSON line with the median backward time per schedule."""
+    import torch
+
+    import chunkwise_delta_rule_gb300 as kda
+    from workloads import CONFIGS, make_config_case
+    dev = torch.device("cuda", 0)
+    cfg = CONFIGS[args.config]
+    case = make_config_case(args.config).to(dev)
+    scheds = [int(x) for x in args.compare.split(",")]
+    probs = {}
+    for sc in scheds:
+        p = kda.make_problem(case.q, case.k, case.v, case.g, case.beta, gate=case.gate, scale=case.scale,
+                             initial_state=case.h0, cu_seqlens=case.cu_seqlens, save_policy=1, schedule=sc)
+        wf = torch.empty(kda.kda_workspace_size(p, False), dtype=torch.uint8, device=dev)
+        wb = torch.empty(kda.kda_workspace_size(p, True), dtype=torch.uint8, device=dev)
+        sv = torch.empty(kda.kda_saved_size(p), dtype=torch.uint8, device=dev)
+        kda.kda_chunk_fwd(p, workspace=wf, saved=sv)
+        probs[sc] = (p, wb, sv)
+    l2 = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def bwd(sc):
+        p, wb, sv = probs[sc]
+        kda.kda_chunk_bwd(p, case.do, case.dht, workspace=wb, saved=sv)
+
+    for _ in range(max(args.warmup, 3)):
+        for sc in scheds:
+            bwd(sc)
+    torch.cuda.synchronize()
+    times = {sc: [] for sc in scheds}
+    rounds = max(args.steps, 30)
+    for r in range(rounds):
+        order = scheds if r % 2 == 0 else scheds[::-1]
+        for sc in order:
+            l2.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            bwd(sc)
+            b.record()
+            times[sc].append((a, b))
+    torch.cuda.synchronize()
+    med = {sc: statistics.median(x.elapsed_time(y) for x, y in v) for sc, v in times.items()}
+    names = {1: "one pass", 9: "joint"}
+    print(json.dumps({"compare": "backward schedules, ABBA", "workload": cfg["name"], "observations": rounds,
+                      "median_bwd_ms": {f"{sc} ({names.get(sc, f'{sc} pieces' if sc >= 2 else 'default')})":
+                                        round(v, 4) for sc, v in med.items()}}), flush=True)
+
+
 def run_e2e(args, case_cpu, dev, kda, K):
     """Same metric through the public API with host buffers: every step copies
     every input from pinned host memory, runs forward and backward, and reads
@@ -862,6 +912,8 @@ def main():
                     help="raw gate and unnormalised q, k: activation and L2 norm inside the operator")
     ap.add_argument("--decode", action="store_true",
                     help="time the token-by-token forward on a decoding step instead of the headline")
+    ap.add_argument("--compare", default="",
+                    help="comma-separated backward schedules (e.g. 9,3,1) timed against each other in ABBA order")
     ap.add_argument("--policy", choices=["save", "recompute"], default="save",
                     help="save: the forward keeps its intermediates for the backward; recompute: the backward rebuilds them")
     args = ap.parse_args()
@@ -869,6 +921,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.compare:
+        run_compare(args)
     elif args.decode:
         run_decode(args)
     else:
