@@ -642,7 +642,8 @@ def run_e2e(args, case_cpu, dev, kda, K):
     def run(d):
         p = kda.make_problem(d["q"], d["k"], d["v"], d.get("g"), d["beta"], gate=case_cpu.gate,
                              scale=case_cpu.scale, initial_state=d.get("h0"), cu_seqlens=d.get("cu_seqlens"),
-                             save_policy=1 if args.policy == "save" else 0)
+                             save_policy=1 if args.policy == "save" else 0,
+                             schedule=args.schedule if args.e2e_schedule < 0 else args.e2e_schedule)
         o, ht, sv = kda.kda_chunk_fwd(p)
         grads = kda.kda_chunk_bwd(p, d["do"], d.get("dht"), saved=sv)
         return [o, ht] + [x for x in grads if x is not None]
@@ -690,21 +691,28 @@ def run_e2e(args, case_cpu, dev, kda, K):
             if not torch.equal(hx, r):
                 worst = max(worst, float((hx.double() - r.double()).abs().max()))
     del ref
-    s0 = torch.cuda.Event(enable_timing=True)
-    s1 = torch.cuda.Event(enable_timing=True)
-    s0.record()
-    for sx in (s_in, s_cp, s_out):
-        sx.wait_event(s0)
-    for st in range(K):
-        step(st)
-    join()
-    s1.record()
-    torch.cuda.synchronize()
-    ms = s0.elapsed_time(s1) / K
+    # three blocks of K steps; the median block is reported (the host link's copy rate varies from
+    # process to process on this machine, and a block shows which mode a run is in)
+    blocks = []
+    for _ in range(3):
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        s0.record()
+        for sx in (s_in, s_cp, s_out):
+            sx.wait_event(s0)
+        for st in range(K):
+            step(st)
+        join()
+        s1.record()
+        torch.cuda.synchronize()
+        blocks.append(s0.elapsed_time(s1) / K)
+    ms = statistics.median(blocks)
     tokens = case_cpu.B * case_cpu.T
     return {"value": round(tokens / (ms * 1e-3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "pipeline": f"{P} piece(s) (whole sequences), input/compute/output streams, double-buffered inputs",
+            "block_ms": [round(b, 4) for b in blocks], "timing": f"median of 3 blocks of {K} steps",
             "pieces_vs_whole_batch": "bitwise equal" if worst == 0.0 else f"max abs diff {worst:.3e}"}
 
 
@@ -899,6 +907,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--schedule", type=int, default=0,
                     help="backward schedule: 0 the library's choice, 1 one pass, P >= 2 time pieces")
+    ap.add_argument("--e2e-schedule", type=int, default=-1,
+                    help="backward schedule of the end-to-end leg (default: the same as --schedule)")
     ap.add_argument("--clocks-csv", default="",
                     help="keep the raw nvidia-smi clock samples of the timed region in this file")
     ap.add_argument("--no-cpu", action="store_true")
