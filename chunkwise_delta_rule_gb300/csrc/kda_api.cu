@@ -24,13 +24,15 @@ struct Dims {
     int per = 0;   // chunks per sequence of an equal-length batch (0: packed sequences)
 };
 
-// Checks the size fields; fills d. Returns KDA_OK or an error (message set). The chunked calls
-// take key widths up to 128; the token-by-token call (chunked = false) checks its own.
-kda_status check_dims(const kda_problem* p, Dims& d, bool chunked = true) {
+// Value widths above the block width (128; 256 when K > 128) run as value blocks.
+int vblock_max(const kda_problem* p) { return p->K > 128 ? 256 : 128; }
+
+// Checks the size fields; fills d. Returns KDA_OK or an error (message set). Key widths up to
+// 256 (the token-by-token call checks its own list on top).
+kda_status check_dims(const kda_problem* p, Dims& d) {
     if (!p) return fail(KDA_ERR_INVALID_ARG, "problem is NULL");
     if (p->B < 1 || p->T < 0 || p->H < 1 || p->K < 1 || p->V < 1)
         return fail(KDA_ERR_INVALID_ARG, "B, H, K, V must be >= 1 and T >= 0");
-    if (chunked && p->K > 128) return fail(KDA_ERR_UNSUPPORTED, "chunked calls: key width above 128 is not built");
     if (p->K > 256) return fail(KDA_ERR_UNSUPPORTED, "key width above 256");
     if (p->V > 4096) return fail(KDA_ERR_UNSUPPORTED, "value width above 4096");
     if (p->H > 65535) return fail(KDA_ERR_UNSUPPORTED, "H > 65535");
@@ -45,8 +47,8 @@ kda_status check_dims(const kda_problem* p, Dims& d, bool chunked = true) {
     if (p->qk_l2norm != 0 && p->qk_l2norm != 1) return fail(KDA_ERR_INVALID_ARG, "qk_l2norm must be 0 or 1");
     if (p->HV != 0 && p->HV != p->H && (p->HV < p->H || p->HV % p->H != 0 || p->HV > 65535))
         return fail(KDA_ERR_INVALID_ARG, "HV must be 0 or a multiple of H (at most 65535)");
-    if ((long long)(p->HV ? p->HV : p->H) * ((p->V + 127) / 128) > 65535)
-        return fail(KDA_ERR_UNSUPPORTED, "value heads times value blocks of 128 above 65535");
+    if ((long long)(p->HV ? p->HV : p->H) * ((p->V + vblock_max(p) - 1) / vblock_max(p)) > 65535)
+        return fail(KDA_ERR_UNSUPPORTED, "value heads times value blocks above 65535");
     if ((p->erase == nullptr) != (p->write == nullptr))
         return fail(KDA_ERR_INVALID_ARG, "erase and write come together (GatedDeltaNet-2)");
     if (p->A_log && p->gate == KDA_GATE_NONE) return fail(KDA_ERR_INVALID_ARG, "A_log needs a gate");
@@ -200,9 +202,10 @@ kda::Shape shape_of(const kda_problem* p, const Dims& d) {
     return s;
 }
 
-// Widths other than K = V = 64 or 128 run zero-padded to D (0: no padding).
+// Widths other than K = V = 64, 128 or 256 run zero-padded to D (0: no padding).
 int pad_width(const kda_problem* p) {
-    if (p->K == p->V && (p->K == 64 || p->K == 128)) return 0;
+    if (p->K == p->V && (p->K == 64 || p->K == 128 || p->K == 256)) return 0;
+    if (p->K > 128) return 256;
     return (p->K <= 64 && p->V <= 64) ? 64 : 128;
 }
 // The padded buffers, in a fixed order after the inner problem's workspace (base NULL: size only).
@@ -285,11 +288,15 @@ size_t gva_bytes(const kda_problem* p, const Dims& d, bool bwd) {
     return one * (bwd ? 4 : 2);   // q, k copies (and, backward, their gradients)
 }
 
-// Value widths above 128: NB = ceil(V / 128) value blocks of width Vb = ceil(V / NB), each run
-// as a value head of its own (the state's value columns evolve independently). Value rows are
-// viewed as [tokens][value heads * NB][Vb] in place when NB * Vb == V, else padded first;
-// per-head inputs repeat per block and their gradients sum over the blocks.
-int vblocks(const kda_problem* p) { return p->V > 128 ? (p->V + 127) / 128 : 1; }
+// Value widths above the block width M (128, or 256 when K > 128): NB = ceil(V / M) value blocks
+// of width Vb = ceil(V / NB), each run as a value head of its own (the state's value columns
+// evolve independently). Value rows are viewed as [tokens][value heads * NB][Vb] in place when
+// NB * Vb == V, else padded first; per-head inputs repeat per block and their gradients sum over
+// the blocks.
+int vblocks(const kda_problem* p) {
+    const int M = vblock_max(p);
+    return p->V > M ? (p->V + M - 1) / M : 1;
+}
 int vblock_width(const kda_problem* p) { return (p->V + vblocks(p) - 1) / vblocks(p); }
 bool vsplit(const kda_problem* p) { return vblocks(p) > 1; }
 long long heads_v(const kda_problem* p) { return p->HV ? p->HV : p->H; }
@@ -1204,7 +1211,7 @@ kda_status kda_chunk_bwd(const kda_problem* p, const void* dout, const float* dh
 
 kda_status kda_recurrent_fwd(const kda_problem* p, void* o, float* ht, int32_t* err, kda_stream_t stream) {
     Dims d;
-    kda_status st = check_dims(p, d, false);
+    kda_status st = check_dims(p, d);
     if (st != KDA_OK) return st;
     if ((st = check_inputs(p, d)) != KDA_OK) return st;
     if (p->save_policy != 0) return fail(KDA_ERR_INVALID_ARG, "the recurrent forward has no saved buffer: use save_policy 0");

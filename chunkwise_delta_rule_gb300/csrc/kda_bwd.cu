@@ -30,20 +30,24 @@ constexpr int SL = 32;  // value columns of S per slice in k_bwd_dstate
 
 // IT: element type of the P, R, S and S+bar inputs: fp32 row-major here, bf16
 // tile images (tile_el) when finishing the wide chunks of the tensor-core
-// path, listed in `list`.
+// path, listed in `list`. Widths are taken in blocks of at most 128 (two at
+// D = 256): the contractions over the value width add up over value blocks,
+// the [BT x D] outputs are formed one key block at a time.
 template <typename TI, typename IT, int D>
 __device__ __forceinline__ void dstate_chunk(int c, int h, const Shape& s, const TI* __restrict__ dout,
                                              const TI* __restrict__ v, const TI* __restrict__ beta, const Table& t,
                                              const IT* __restrict__ Pin, const IT* __restrict__ Rin,
                                              const IT* __restrict__ Sin, const IT* __restrict__ SBin, const Bwd& b,
                                              TI* __restrict__ dv, const Gdn2& gd) {
-    constexpr int LD = D + 1, LS = SL + 1;
+    constexpr int DC = D > 128 ? 128 : D;   // columns per block
+    constexpr int NB = D / DC;              // blocks
+    constexpr int LD = DC + 1, LS = SL + 1;
     extern __shared__ float smem[];
-    float* sO = smem;              // [BT][LD] dO
+    float* sO = smem;              // [BT][LD] dO, one value block
     float* sP = sO + BT * LD;      // [BT][LD] P
     float* sR = sP + BT * LD;      // [BT][LD] R
-    float* sS = sR + BT * LD;      // [D][LS] slice of S
-    float* sT = sS + D * LS;       // [D][LS] slice of S+bar
+    float* sS = sR + BT * LD;      // [DC][LS] slice of S (one key block)
+    float* sT = sS + DC * LS;      // [DC][LS] slice of S+bar
 
     const int tid = threadIdx.x;
     const int len = t.chunk_len[c];
@@ -56,46 +60,66 @@ __device__ __forceinline__ void dstate_chunk(int c, int h, const Shape& s, const
     constexpr bool IMG = sizeof(IT) == 2;
     const IT* P = Pin + ch * BT * D;
     const IT* R = Rin + ch * BT * D;
-    for (int idx = tid; idx < BT * D; idx += NTHREADS) {
-        const int r = idx / D, col = idx % D;
-        const int e = IMG ? tile_el(BT, r, col) : idx;
-        sO[r * LD + col] = (r < len) ? ld(dout + ((size_t)(tok0 + r) * H + h) * D + col) : 0.f;
-        sP[r * LD + col] = ld(P + e);
-        sR[r * LD + col] = ld(R + e);
-    }
-    __syncthreads();
-    // dv = beta P and <v_i, P_i>, one warp per row (GatedDeltaNet-2: dv = w .* P, dw = v .* P)
-    const TI* wr = static_cast<const TI*>(gd.write);
-    for (int r = warp; r < BT; r += NTHREADS / 32) {
-        float acc = 0.f;
-        if (r < len) {
-            const size_t tok = (size_t)(tok0 + r) * H + h;
-            const float bt = wr ? 0.f : ld(beta + tok);
-            for (int col = lane; col < D; col += 32) {
-                const float p = sP[r * LD + col], vv = ld(v + tok * D + col);
-                if (wr) {
-                    st(dv + tok * D + col, ld(wr + tok * D + col) * p);
-                    st(static_cast<TI*>(gd.dwrite) + tok * D + col, vv * p);
-                } else {
-                    acc = fmaf(vv, p, acc);
-                    st(dv + tok * D + col, bt * p);
-                }
-            }
+    // dO, P and R of value columns v0 .. v0+DC-1
+    auto load_block = [&](int v0) {
+        for (int idx = tid; idx < BT * DC; idx += NTHREADS) {
+            const int r = idx / DC, col = v0 + idx % DC;
+            const int e = IMG ? tile_el(BT, r, col) : r * D + col;
+            const int o = r * LD + idx % DC;
+            sO[o] = (r < len) ? ld(dout + ((size_t)(tok0 + r) * H + h) * D + col) : 0.f;
+            sP[o] = ld(P + e);
+            sR[o] = ld(R + e);
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        if (lane == 0) b.DBW[ch * BT + r] = acc;
-    }
+    };
+    // ---- value-width contractions, value block by value block:
+    // dv = beta P and <v_i, P_i>, one warp per row (GatedDeltaNet-2: dv = w .* P, dw = v .* P);
     // D = -L_<(P R^T), H_q = L_<=(dO R^T)
     {
+        const TI* wr = static_cast<const TI*>(gd.write);
+        constexpr int RW = BT / (NTHREADS / 32);   // rows per warp
+        float dbw[RW];
+#pragma unroll
+        for (int i = 0; i < RW; ++i) dbw[i] = 0.f;
         using TMp = TileMap<BT, BT, 8, 2>;
         float acc[8][2], acc2[8][2];
         zero(acc);
         zero(acc2);
-        tile_gemm<BT, BT, 8, 2>(acc, 0, D, [&](int m, int kk) { return sP[m * LD + kk]; },
-                                [&](int kk, int nn) { return sR[nn * LD + kk]; });
-        tile_gemm<BT, BT, 8, 2>(acc2, 0, D, [&](int m, int kk) { return sO[m * LD + kk]; },
-                                [&](int kk, int nn) { return sR[nn * LD + kk]; });
+        for (int vb = 0; vb < NB; ++vb) {
+            const int v0 = vb * DC;
+            if (vb > 0) __syncthreads();   // the previous block's tiles are no longer read
+            load_block(v0);
+            __syncthreads();
+#pragma unroll
+            for (int i = 0; i < RW; ++i) {
+                const int r = warp + i * (NTHREADS / 32);
+                if (r < len) {
+                    const size_t tok = (size_t)(tok0 + r) * H + h;
+                    const float bt = wr ? 0.f : ld(beta + tok);
+                    for (int cc = lane; cc < DC; cc += 32) {
+                        const int col = v0 + cc;
+                        const float p = sP[r * LD + cc], vv = ld(v + tok * D + col);
+                        if (wr) {
+                            st(dv + tok * D + col, ld(wr + tok * D + col) * p);
+                            st(static_cast<TI*>(gd.dwrite) + tok * D + col, vv * p);
+                        } else {
+                            dbw[i] = fmaf(vv, p, dbw[i]);
+                            st(dv + tok * D + col, bt * p);
+                        }
+                    }
+                }
+            }
+            tile_gemm<BT, BT, 8, 2>(acc, 0, DC, [&](int m, int kk) { return sP[m * LD + kk]; },
+                                    [&](int kk, int nn) { return sR[nn * LD + kk]; });
+            tile_gemm<BT, BT, 8, 2>(acc2, 0, DC, [&](int m, int kk) { return sO[m * LD + kk]; },
+                                    [&](int kk, int nn) { return sR[nn * LD + kk]; });
+        }
+#pragma unroll
+        for (int i = 0; i < RW; ++i) {
+            float x = dbw[i];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+            if (lane == 0) b.DBW[ch * BT + warp + i * (NTHREADS / 32)] = x;
+        }
         float* DM = b.DM + ch * BT * BT;
         float* HQ = b.HQ + ch * BT * BT;
 #pragma unroll
@@ -107,61 +131,78 @@ __device__ __forceinline__ void dstate_chunk(int c, int h, const Shape& s, const
                 HQ[m * BT + nn] = (nn <= m) ? acc2[ii][jj] : 0.f;
             }
     }
-    // dO S^T, -P S^T, R S+bar^T over value slices; rowsum(S .* S+bar)
-    constexpr int TN = D / 32;
-    using TK = TileMap<BT, D, 8, TN>;
-    float aQ[8][TN], aP[8][TN], aF[8][TN];
-    zero(aQ);
-    zero(aP);
-    zero(aF);
-    constexpr int TPR = NTHREADS / D;          // threads per key row for the rowsum
+    // ---- dO S^T, -P S^T, R S+bar^T and rowsum(S .* S+bar), one key block at a
+    // time, summed over value slices
+    constexpr int TN = DC / 32;
+    using TK = TileMap<BT, DC, 8, TN>;
+    constexpr int TPR = NTHREADS / DC;          // threads per key row for the rowsum
     const int kr = tid / TPR, kpart = tid % TPR;
-    float lam = 0.f;
     const IT* SIN = Sin + ch * D * D;
     const IT* SBP = SBin + ch * D * D;
-    for (int vs = 0; vs < D; vs += SL) {
-        __syncthreads();
-        for (int idx = tid; idx < D * SL; idx += NTHREADS) {
-            const int r = idx / SL, cc = idx % SL;
-            const size_t e = IMG ? (size_t)tile_el(D, r, vs + cc) : (size_t)r * D + vs + cc;
-            sS[r * LS + cc] = ld(SIN + e);
-            sT[r * LS + cc] = ld(SBP + e);
-        }
-        __syncthreads();
-        tile_gemm<BT, D, 8, TN>(aQ, 0, SL, [&](int m, int kk) { return sO[m * LD + vs + kk]; },
-                                [&](int kk, int nn) { return sS[nn * LS + kk]; });
-        tile_gemm<BT, D, 8, TN>(aP, 0, SL, [&](int m, int kk) { return sP[m * LD + vs + kk]; },
-                                [&](int kk, int nn) { return sS[nn * LS + kk]; });
-        tile_gemm<BT, D, 8, TN>(aF, 0, SL, [&](int m, int kk) { return sR[m * LD + vs + kk]; },
-                                [&](int kk, int nn) { return sT[nn * LS + kk]; });
-        for (int cc = kpart; cc < SL; cc += TPR) lam = fmaf(sS[kr * LS + cc], sT[kr * LS + cc], lam);
-    }
     float* QS = b.QS + ch * BT * D;
     float* PS = b.PS + ch * BT * D;
     float* FB = b.FB + ch * BT * D;
-#pragma unroll
-    for (int ii = 0; ii < 8; ++ii)
-#pragma unroll
-        for (int jj = 0; jj < TN; ++jj) {
-            const size_t o = (size_t)TK::row(ii) * D + TK::col(jj);
-            QS[o] = aQ[ii][jj];
-            PS[o] = -aP[ii][jj];
-            FB[o] = aF[ii][jj];
+    for (int kb = 0; kb < NB; ++kb) {
+        const int k0 = kb * DC;
+        float aQ[8][TN], aP[8][TN], aF[8][TN];
+        zero(aQ);
+        zero(aP);
+        zero(aF);
+        float lam = 0.f;
+        for (int vb = 0; vb < NB; ++vb) {
+            const int v0 = vb * DC;
+            if (NB > 1) {
+                __syncthreads();
+                load_block(v0);
+            }
+            for (int vs = 0; vs < DC; vs += SL) {
+                __syncthreads();
+                for (int idx = tid; idx < DC * SL; idx += NTHREADS) {
+                    const int r = k0 + idx / SL, cc = v0 + vs + idx % SL;
+                    const size_t e = IMG ? (size_t)tile_el(D, r, cc) : (size_t)r * D + cc;
+                    sS[(idx / SL) * LS + idx % SL] = ld(SIN + e);
+                    sT[(idx / SL) * LS + idx % SL] = ld(SBP + e);
+                }
+                __syncthreads();
+                tile_gemm<BT, DC, 8, TN>(aQ, 0, SL, [&](int m, int kk) { return sO[m * LD + vs + kk]; },
+                                         [&](int kk, int nn) { return sS[nn * LS + kk]; });
+                tile_gemm<BT, DC, 8, TN>(aP, 0, SL, [&](int m, int kk) { return sP[m * LD + vs + kk]; },
+                                         [&](int kk, int nn) { return sS[nn * LS + kk]; });
+                tile_gemm<BT, DC, 8, TN>(aF, 0, SL, [&](int m, int kk) { return sR[m * LD + vs + kk]; },
+                                         [&](int kk, int nn) { return sT[nn * LS + kk]; });
+                for (int cc = kpart; cc < SL; cc += TPR) lam = fmaf(sS[kr * LS + cc], sT[kr * LS + cc], lam);
+            }
         }
 #pragma unroll
-    for (int o = TPR / 2; o > 0; o >>= 1) lam += __shfl_xor_sync(0xffffffffu, lam, o);
-    if (kpart == 0) b.LAMB[ch * D + kr] = lam;
+        for (int ii = 0; ii < 8; ++ii)
+#pragma unroll
+            for (int jj = 0; jj < TN; ++jj) {
+                const size_t o = (size_t)TK::row(ii) * D + k0 + TK::col(jj);
+                QS[o] = aQ[ii][jj];
+                PS[o] = -aP[ii][jj];
+                FB[o] = aF[ii][jj];
+            }
+#pragma unroll
+        for (int o = TPR / 2; o > 0; o >>= 1) lam += __shfl_xor_sync(0xffffffffu, lam, o);
+        if (kpart == 0) b.LAMB[ch * D + k0 + kr] = lam;
+    }
 }
 
+// Features are taken in column blocks of at most 128 (two passes at D = 256);
+// every contraction here runs over tokens, so the blocks are independent but
+// for the per-row sums (dbeta, the scalar gate's G_bar), carried across them.
+// The gate-range dispatch is made per block.
 template <typename TI, int D, int GATE>
 __device__ __forceinline__ void intra_chunk(int c, int h, const Shape& s, const TI* __restrict__ q,
                                             const TI* __restrict__ k, const TI* __restrict__ beta,
                                             const float* __restrict__ g, const Table& t, const Bwd& b,
                                             TI* __restrict__ dq, TI* __restrict__ dk, TI* __restrict__ dbeta,
                                             float* __restrict__ dg, const Gdn2& gd) {
-    constexpr int LD = D + 1, LA = BT + 1;
+    constexpr int DC = D > 128 ? 128 : D;   // feature columns per pass
+    constexpr int NB = D / DC;              // passes
+    constexpr int LD = DC + 1, LA = BT + 1;
     extern __shared__ float smem[];
-    float* sK = smem;               // [BT][LD] keys
+    float* sK = smem;               // [BT][LD] keys of the column block
     float* sQ = sK + BT * LD;       // [BT][LD] queries
     float* sG = sQ + BT * LD;       // [BT][LD] cumulative log2-decay
     float* sF3 = sG + BT * LD;      // [BT][LD] operand
@@ -169,8 +210,8 @@ __device__ __forceinline__ void intra_chunk(int c, int h, const Shape& s, const 
     float* sDM = sF4 + BT * LD;     // [BT][LA] D
     float* sHQ = sDM + BT * LA;     // [BT][LA] H_q
     float* sBeta = sHQ + BT * LA;   // [BT]
-    float* sC = sBeta + BT;         // [D] center of each feature
-    float* sRow = sC + D;           // [BT] per-row reductions
+    float* sC = sBeta + BT;         // [DC] center of each feature
+    float* sRow = sC + DC;          // [BT] per-row reductions
 
     const int tid = threadIdx.x;
     const int len = t.chunk_len[c];
@@ -181,20 +222,6 @@ __device__ __forceinline__ void intra_chunk(int c, int h, const Shape& s, const 
     const float scale = s.scale;
     const int lane = tid & 31, warp = tid >> 5;
 
-    for (int idx = tid; idx < BT * D; idx += NTHREADS) {
-        const int r = idx / D, col = idx % D;
-        float kv = 0.f, qv = 0.f, gv = 0.f;
-        if (r < len) {
-            const size_t off = ((size_t)(tok0 + r) * H + h) * D + col;
-            kv = ld(k + off);
-            qv = ld(q + off);
-            if (GATE == 2) gv = g[off] * LOG2E;
-            if (GATE == 1) gv = g[(size_t)(tok0 + r) * H + h] * LOG2E;
-        }
-        sK[r * LD + col] = kv;
-        sQ[r * LD + col] = qv;
-        sG[r * LD + col] = gv;
-    }
     {
         const float* DM = b.DM + ch * BT * BT;
         const float* HQ = b.HQ + ch * BT * BT;
@@ -206,224 +233,272 @@ __device__ __forceinline__ void intra_chunk(int c, int h, const Shape& s, const 
     if (tid < BT) sBeta[tid] = (tid < len && !gd.erase) ? ld(beta + (size_t)(tok0 + tid) * H + h) : 0.f;
     // GatedDeltaNet-2: the erase vector takes beta's place on the key side (E = b .* K exp(G))
     const TI* er = static_cast<const TI*>(gd.erase);
-    auto ebeta = [&](int r, int col) {
-        return er ? ((r < len) ? ld(er + ((size_t)(tok0 + r) * H + h) * D + col) : 0.f) : sBeta[r];
+    auto ebeta = [&](int r, int gcol) {
+        return er ? ((r < len) ? ld(er + ((size_t)(tok0 + r) * H + h) * D + gcol) : 0.f) : sBeta[r];
     };
-    __syncthreads();
-    int wide_col = 0;
-    if (tid < D) {
-        float acc = 0.f;
-        for (int r = 0; r < BT; ++r) {
-            acc += sG[r * LD + tid];
-            sG[r * LD + tid] = acc;
-        }
-        float hi = sG[tid], lo = sG[tid];
-        for (int r = 1; r < len; ++r) {
-            hi = fmaxf(hi, sG[r * LD + tid]);
-            lo = fminf(lo, sG[r * LD + tid]);
-        }
-        sC[tid] = (GATE == 2) ? 0.5f * (hi + lo) : 0.f;   // midpoint center
-        wide_col = (GATE == 2) && (hi - lo > CENTER_RANGE_LOG2);
-    }
-    // gate-range dispatch: one wide feature sends the chunk to the sub-chunk path
-    const bool wide = __syncthreads_or(wide_col) != 0;
-    if (GATE == 1) {
-        // scalar gate: fold the exact pairwise decay exp(G_i - G_j) (<= 1) into D and H_q
-        for (int idx = tid; idx < BT * BT; idx += NTHREADS) {
-            const int i = idx / BT, j = idx % BT;
-            if (j <= i) {
-                const float e = exp2f(sG[i * LD] - sG[j * LD]);
-                sDM[i * LA + j] *= e;
-                sHQ[i * LA + j] *= e;
-            }
-        }
-        __syncthreads();
-    }
+    const float* QS = b.QS + ch * BT * D;
+    const float* PS = b.PS + ch * BT * D;
+    const float* FB = b.FB + ch * BT * D;
+    constexpr int TN = DC / 32;
+    using TK = TileMap<BT, DC, 8, TN>;
+    float rowacc[8];
+#pragma unroll
+    for (int ii = 0; ii < 8; ++ii) rowacc[ii] = 0.f;
 
-    constexpr int TN = D / 32;
-    using TK = TileMap<BT, D, 8, TN>;
-    float aQ[8][TN], aE[8][TN], aY[8][TN];
-    zero(aQ);
-    zero(aE);
-    zero(aY);
-    // factors: unit for scalar / no gate (already folded), centered otherwise
-    auto alpha = [&](int i, int col) { return GATE == 2 ? exp2f(sG[i * LD + col] - sC[col]) : 1.f; };
-    auto zeta = [&](int i, int col) { return GATE == 2 ? exp2f(sC[col] - sG[i * LD + col]) : 1.f; };
-
-    if (!wide) {
-        // T_q = H_q (K zeta), T_e = D (K zeta)
-        for (int idx = tid; idx < BT * D; idx += NTHREADS) {
-            const int r = idx / D, col = idx % D;
-            sF3[r * LD + col] = sK[r * LD + col] * zeta(r, col);
-        }
-        __syncthreads();
-        tile_gemm<BT, D, 8, TN>(aQ, 0, BT, [&](int m, int kk) { return sHQ[m * LA + kk]; },
-                                [&](int kk, int nn) { return sF3[kk * LD + nn]; });
-        tile_gemm<BT, D, 8, TN>(aE, 0, BT, [&](int m, int kk) { return sDM[m * LA + kk]; },
-                                [&](int kk, int nn) { return sF3[kk * LD + nn]; });
-#pragma unroll
-        for (int ii = 0; ii < 8; ++ii)
-#pragma unroll
-            for (int jj = 0; jj < TN; ++jj) {
-                const float a = alpha(TK::row(ii), TK::col(jj));
-                aQ[ii][jj] *= a;
-                aE[ii][jj] *= a;
+    for (int cb = 0; cb < NB; ++cb) {
+        const int c0 = cb * DC;
+        if (cb > 0) __syncthreads();   // the previous block's tiles are no longer read
+        for (int idx = tid; idx < BT * DC; idx += NTHREADS) {
+            const int r = idx / DC, col = idx % DC;
+            float kv = 0.f, qv = 0.f, gv = 0.f;
+            if (r < len) {
+                const size_t off = ((size_t)(tok0 + r) * H + h) * D + c0 + col;
+                kv = ld(k + off);
+                qv = ld(q + off);
+                if (GATE == 2) gv = g[off] * LOG2E;
+                if (GATE == 1) gv = g[(size_t)(tok0 + r) * H + h] * LOG2E;
             }
-        __syncthreads();
-        // T_y = D^T (beta K alpha) + H_q^T (scale Q alpha)
-        for (int idx = tid; idx < BT * D; idx += NTHREADS) {
-            const int r = idx / D, col = idx % D;
-            const float a = alpha(r, col);
-            sF3[r * LD + col] = ebeta(r, col) * sK[r * LD + col] * a;
-            sF4[r * LD + col] = scale * sQ[r * LD + col] * a;
+            sK[r * LD + col] = kv;
+            sQ[r * LD + col] = qv;
+            sG[r * LD + col] = gv;
         }
         __syncthreads();
-        tile_gemm<BT, D, 8, TN>(aY, 0, BT, [&](int m, int kk) { return sDM[kk * LA + m]; },
-                                [&](int kk, int nn) { return sF3[kk * LD + nn]; });
-        tile_gemm<BT, D, 8, TN>(aY, 0, BT, [&](int m, int kk) { return sHQ[kk * LA + m]; },
-                                [&](int kk, int nn) { return sF4[kk * LD + nn]; });
-#pragma unroll
-        for (int ii = 0; ii < 8; ++ii)
-#pragma unroll
-            for (int jj = 0; jj < TN; ++jj) aY[ii][jj] *= zeta(TK::row(ii), TK::col(jj));
-    } else {
-        // Strong gates: 16-token sub-chunks. Receiving rows i of sub-chunk sb
-        // take earlier sub-chunks with the anchor G at the first row of sb
-        // (both factors <= 1) and the diagonal block with its midpoint row.
-        // A thread's rows in sub-chunk sb are TK::row(2 sb) and TK::row(2 sb + 1).
-        const int tm = TK::tm(), tn = TK::tn();
-        for (int sb = 0; sb < BT / BC; ++sb) {
-            if (sb * BC >= len) break;
-            const int ra = sb * BC, rm = sb * BC + BC / 2;
-            __syncthreads();
-            for (int idx = tid; idx < BT * D; idx += NTHREADS) {
-                const int j = idx / D, col = idx % D;
-                float val = 0.f;
-                if (j < ra) val = sK[j * LD + col] * exp2f(sG[ra * LD + col] - sG[j * LD + col]);
-                else if (j < ra + BC) val = sK[j * LD + col] * exp2f(sG[rm * LD + col] - sG[j * LD + col]);
-                sF3[j * LD + col] = val;
+        int wide_col = 0;
+        if (tid < DC) {
+            float acc = 0.f;
+            for (int r = 0; r < BT; ++r) {
+                acc += sG[r * LD + tid];
+                sG[r * LD + tid] = acc;
+            }
+            float hi = sG[tid], lo = sG[tid];
+            for (int r = 1; r < len; ++r) {
+                hi = fmaxf(hi, sG[r * LD + tid]);
+                lo = fminf(lo, sG[r * LD + tid]);
+            }
+            sC[tid] = (GATE == 2) ? 0.5f * (hi + lo) : 0.f;   // midpoint center
+            wide_col = (GATE == 2) && (hi - lo > CENTER_RANGE_LOG2);
+        }
+        // gate-range dispatch: one wide feature sends the block to the sub-chunk path
+        const bool wide = __syncthreads_or(wide_col) != 0;
+        if (GATE == 1 && cb == 0) {
+            // scalar gate: fold the exact pairwise decay exp(G_i - G_j) (<= 1) into D and H_q
+            for (int idx = tid; idx < BT * BT; idx += NTHREADS) {
+                const int i = idx / BT, j = idx % BT;
+                if (j <= i) {
+                    const float e = exp2f(sG[i * LD] - sG[j * LD]);
+                    sDM[i * LA + j] *= e;
+                    sHQ[i * LA + j] *= e;
+                }
             }
             __syncthreads();
+        }
+
+        float aQ[8][TN], aE[8][TN], aY[8][TN];
+        zero(aQ);
+        zero(aE);
+        zero(aY);
+        // factors: unit for scalar / no gate (already folded), centered otherwise
+        auto alpha = [&](int i, int col) { return GATE == 2 ? exp2f(sG[i * LD + col] - sC[col]) : 1.f; };
+        auto zeta = [&](int i, int col) { return GATE == 2 ? exp2f(sC[col] - sG[i * LD + col]) : 1.f; };
+
+        if (!wide) {
+            // T_q = H_q (K zeta), T_e = D (K zeta)
+            for (int idx = tid; idx < BT * DC; idx += NTHREADS) {
+                const int r = idx / DC, col = idx % DC;
+                sF3[r * LD + col] = sK[r * LD + col] * zeta(r, col);
+            }
+            __syncthreads();
+            tile_gemm<BT, DC, 8, TN>(aQ, 0, BT, [&](int m, int kk) { return sHQ[m * LA + kk]; },
+                                     [&](int kk, int nn) { return sF3[kk * LD + nn]; });
+            tile_gemm<BT, DC, 8, TN>(aE, 0, BT, [&](int m, int kk) { return sDM[m * LA + kk]; },
+                                     [&](int kk, int nn) { return sF3[kk * LD + nn]; });
 #pragma unroll
-            for (int which = 0; which < 2; ++which) {
-                const float* Mx = which == 0 ? sHQ : sDM;
+            for (int ii = 0; ii < 8; ++ii)
+#pragma unroll
+                for (int jj = 0; jj < TN; ++jj) {
+                    const float a = alpha(TK::row(ii), TK::col(jj));
+                    aQ[ii][jj] *= a;
+                    aE[ii][jj] *= a;
+                }
+            __syncthreads();
+            // T_y = D^T (beta K alpha) + H_q^T (scale Q alpha)
+            for (int idx = tid; idx < BT * DC; idx += NTHREADS) {
+                const int r = idx / DC, col = idx % DC;
+                const float a = alpha(r, col);
+                sF3[r * LD + col] = ebeta(r, c0 + col) * sK[r * LD + col] * a;
+                sF4[r * LD + col] = scale * sQ[r * LD + col] * a;
+            }
+            __syncthreads();
+            tile_gemm<BT, DC, 8, TN>(aY, 0, BT, [&](int m, int kk) { return sDM[kk * LA + m]; },
+                                     [&](int kk, int nn) { return sF3[kk * LD + nn]; });
+            tile_gemm<BT, DC, 8, TN>(aY, 0, BT, [&](int m, int kk) { return sHQ[kk * LA + m]; },
+                                     [&](int kk, int nn) { return sF4[kk * LD + nn]; });
+#pragma unroll
+            for (int ii = 0; ii < 8; ++ii)
+#pragma unroll
+                for (int jj = 0; jj < TN; ++jj) aY[ii][jj] *= zeta(TK::row(ii), TK::col(jj));
+        } else {
+            // Strong gates: 16-token sub-chunks. Receiving rows i of sub-chunk sb
+            // take earlier sub-chunks with the anchor G at the first row of sb
+            // (both factors <= 1) and the diagonal block with its midpoint row.
+            // A thread's rows in sub-chunk sb are TK::row(2 sb) and TK::row(2 sb + 1).
+            const int tm = TK::tm(), tn = TK::tn();
+            for (int sb = 0; sb < BT / BC; ++sb) {
+                if (sb * BC >= len) break;
+                const int ra = sb * BC, rm = sb * BC + BC / 2;
+                __syncthreads();
+                for (int idx = tid; idx < BT * DC; idx += NTHREADS) {
+                    const int j = idx / DC, col = idx % DC;
+                    float val = 0.f;
+                    if (j < ra) val = sK[j * LD + col] * exp2f(sG[ra * LD + col] - sG[j * LD + col]);
+                    else if (j < ra + BC) val = sK[j * LD + col] * exp2f(sG[rm * LD + col] - sG[j * LD + col]);
+                    sF3[j * LD + col] = val;
+                }
+                __syncthreads();
+#pragma unroll
+                for (int which = 0; which < 2; ++which) {
+                    const float* Mx = which == 0 ? sHQ : sDM;
+                    float off[2][TN], dia[2][TN];
+                    zero(off);
+                    zero(dia);
+                    for (int kk = 0; kk < ra + BC; ++kk) {
+                        float a[2], bv[TN];
+#pragma unroll
+                        for (int r = 0; r < 2; ++r) a[r] = Mx[(tm + 8 * (2 * sb + r)) * LA + kk];
+#pragma unroll
+                        for (int jj = 0; jj < TN; ++jj) bv[jj] = sF3[kk * LD + tn + 32 * jj];
+#pragma unroll
+                        for (int r = 0; r < 2; ++r)
+#pragma unroll
+                            for (int jj = 0; jj < TN; ++jj) {
+                                if (kk < ra) off[r][jj] = fmaf(a[r], bv[jj], off[r][jj]);
+                                else dia[r][jj] = fmaf(a[r], bv[jj], dia[r][jj]);
+                            }
+                    }
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const int i = tm + 8 * (2 * sb + r);
+#pragma unroll
+                        for (int jj = 0; jj < TN; ++jj) {
+                            const int col = tn + 32 * jj;
+                            const float gi = sG[i * LD + col];
+                            const float val = exp2f(gi - sG[ra * LD + col]) * off[r][jj] +
+                                              exp2f(gi - sG[rm * LD + col]) * dia[r][jj];
+                            if (which == 0) aQ[2 * sb + r][jj] = val;
+                            else aE[2 * sb + r][jj] = val;
+                        }
+                    }
+                }
+            }
+            // Transposed contractions: output rows j of sub-chunk sb; summed rows i
+            // of later sub-chunks use the anchor G at the last row of sb, the
+            // diagonal block its midpoint row.
+            for (int sb = 0; sb < BT / BC; ++sb) {
+                if (sb * BC >= len) break;
+                const int ra = sb * BC, re = sb * BC + BC - 1, rm = sb * BC + BC / 2;
+                __syncthreads();
+                for (int idx = tid; idx < BT * DC; idx += NTHREADS) {
+                    const int i = idx / DC, col = idx % DC;
+                    float e = 0.f;
+                    if (i >= ra + BC) e = exp2f(sG[i * LD + col] - sG[re * LD + col]);
+                    else if (i >= ra) e = exp2f(sG[i * LD + col] - sG[rm * LD + col]);
+                    sF3[i * LD + col] = ebeta(i, c0 + col) * sK[i * LD + col] * e;
+                    sF4[i * LD + col] = scale * sQ[i * LD + col] * e;
+                }
+                __syncthreads();
                 float off[2][TN], dia[2][TN];
                 zero(off);
                 zero(dia);
-                for (int kk = 0; kk < ra + BC; ++kk) {
-                    float a[2], bv[TN];
+                for (int kk = ra; kk < BT; ++kk) {
+                    float a1[2], a2[2], b1[TN], b2[TN];
 #pragma unroll
-                    for (int r = 0; r < 2; ++r) a[r] = Mx[(tm + 8 * (2 * sb + r)) * LA + kk];
+                    for (int r = 0; r < 2; ++r) {
+                        const int j = tm + 8 * (2 * sb + r);
+                        a1[r] = sDM[kk * LA + j];
+                        a2[r] = sHQ[kk * LA + j];
+                    }
 #pragma unroll
-                    for (int jj = 0; jj < TN; ++jj) bv[jj] = sF3[kk * LD + tn + 32 * jj];
+                    for (int jj = 0; jj < TN; ++jj) {
+                        b1[jj] = sF3[kk * LD + tn + 32 * jj];
+                        b2[jj] = sF4[kk * LD + tn + 32 * jj];
+                    }
 #pragma unroll
                     for (int r = 0; r < 2; ++r)
 #pragma unroll
                         for (int jj = 0; jj < TN; ++jj) {
-                            if (kk < ra) off[r][jj] = fmaf(a[r], bv[jj], off[r][jj]);
-                            else dia[r][jj] = fmaf(a[r], bv[jj], dia[r][jj]);
+                            const float x = fmaf(a1[r], b1[jj], a2[r] * b2[jj]);
+                            if (kk >= ra + BC) off[r][jj] += x;
+                            else dia[r][jj] += x;
                         }
                 }
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
-                    const int i = tm + 8 * (2 * sb + r);
+                    const int j = tm + 8 * (2 * sb + r);
 #pragma unroll
                     for (int jj = 0; jj < TN; ++jj) {
                         const int col = tn + 32 * jj;
-                        const float gi = sG[i * LD + col];
-                        const float val = exp2f(gi - sG[ra * LD + col]) * off[r][jj] +
-                                          exp2f(gi - sG[rm * LD + col]) * dia[r][jj];
-                        if (which == 0) aQ[2 * sb + r][jj] = val;
-                        else aE[2 * sb + r][jj] = val;
+                        const float gj = sG[j * LD + col];
+                        aY[2 * sb + r][jj] = exp2f(sG[re * LD + col] - gj) * off[r][jj] +
+                                             exp2f(sG[rm * LD + col] - gj) * dia[r][jj];
                     }
                 }
             }
         }
-        // Transposed contractions: output rows j of sub-chunk sb; summed rows i
-        // of later sub-chunks use the anchor G at the last row of sb, the
-        // diagonal block its midpoint row.
-        for (int sb = 0; sb < BT / BC; ++sb) {
-            if (sb * BC >= len) break;
-            const int ra = sb * BC, re = sb * BC + BC - 1, rm = sb * BC + BC / 2;
-            __syncthreads();
-            for (int idx = tid; idx < BT * D; idx += NTHREADS) {
-                const int i = idx / D, col = idx % D;
-                float e = 0.f;
-                if (i >= ra + BC) e = exp2f(sG[i * LD + col] - sG[re * LD + col]);
-                else if (i >= ra) e = exp2f(sG[i * LD + col] - sG[rm * LD + col]);
-                sF3[i * LD + col] = ebeta(i, col) * sK[i * LD + col] * e;
-                sF4[i * LD + col] = scale * sQ[i * LD + col] * e;
-            }
-            __syncthreads();
-            float off[2][TN], dia[2][TN];
-            zero(off);
-            zero(dia);
-            for (int kk = ra; kk < BT; ++kk) {
-                float a1[2], a2[2], b1[TN], b2[TN];
-#pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    const int j = tm + 8 * (2 * sb + r);
-                    a1[r] = sDM[kk * LA + j];
-                    a2[r] = sHQ[kk * LA + j];
-                }
-#pragma unroll
-                for (int jj = 0; jj < TN; ++jj) {
-                    b1[jj] = sF3[kk * LD + tn + 32 * jj];
-                    b2[jj] = sF4[kk * LD + tn + 32 * jj];
-                }
-#pragma unroll
-                for (int r = 0; r < 2; ++r)
-#pragma unroll
-                    for (int jj = 0; jj < TN; ++jj) {
-                        const float x = fmaf(a1[r], b1[jj], a2[r] * b2[jj]);
-                        if (kk >= ra + BC) off[r][jj] += x;
-                        else dia[r][jj] += x;
-                    }
-            }
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                const int j = tm + 8 * (2 * sb + r);
-#pragma unroll
-                for (int jj = 0; jj < TN; ++jj) {
-                    const int col = tn + 32 * jj;
-                    const float gj = sG[j * LD + col];
-                    aY[2 * sb + r][jj] = exp2f(sG[re * LD + col] - gj) * off[r][jj] +
-                                         exp2f(sG[rm * LD + col] - gj) * dia[r][jj];
-                }
-            }
-        }
-    }
-    __syncthreads();  // operand buffers free from here on
+        __syncthreads();  // operand buffers free from here on
 
-    // ---- chain rule (a12)
-    const float* QS = b.QS + ch * BT * D;
-    const float* PS = b.PS + ch * BT * D;
-    const float* FB = b.FB + ch * BT * D;
-    const float* gl2 = sG + (len - 1) * LD;
-    float rowacc[8];
+        // ---- chain rule (a12) for the block's features
+        const float* gl2 = sG + (len - 1) * LD;
 #pragma unroll
-    for (int ii = 0; ii < 8; ++ii) rowacc[ii] = 0.f;
+        for (int ii = 0; ii < 8; ++ii) {
+            const int m = TK::row(ii);
 #pragma unroll
-    for (int ii = 0; ii < 8; ++ii) {
-        const int m = TK::row(ii);
-#pragma unroll
-        for (int jj = 0; jj < TN; ++jj) {
-            const int col = TK::col(jj);
-            const size_t o = (size_t)m * D + col;
-            const float gm = sG[m * LD + col];
-            const float gam = exp2f(gm);
-            const float Qt = aQ[ii][jj] + gam * QS[o];                    // gamma * Q_g_bar
-            const float Et = aE[ii][jj] + gam * PS[o];                    // gamma * E_bar
-            const float Yt = aY[ii][jj] + FB[o] * exp2f(gl2[col] - gm);   // Y_bar / gamma
-            const float kv = sK[m * LD + col], qv = sQ[m * LD + col], bt = ebeta(m, col);
-            if (m < len) {
-                const size_t go = ((size_t)(tok0 + m) * H + h) * D + col;
-                st(dq + go, scale * Qt);
-                st(dk + go, bt * Et + Yt);
-                if (er) st(static_cast<TI*>(gd.derase) + go, kv * Et);   // db = K exp(G) .* E_bar
+            for (int jj = 0; jj < TN; ++jj) {
+                const int col = TK::col(jj);
+                const size_t o = (size_t)m * D + c0 + col;
+                const float gm = sG[m * LD + col];
+                const float gam = exp2f(gm);
+                const float Qt = aQ[ii][jj] + gam * QS[o];                    // gamma * Q_g_bar
+                const float Et = aE[ii][jj] + gam * PS[o];                    // gamma * E_bar
+                const float Yt = aY[ii][jj] + FB[o] * exp2f(gl2[col] - gm);   // Y_bar / gamma
+                const float kv = sK[m * LD + col], qv = sQ[m * LD + col], bt = ebeta(m, c0 + col);
+                if (m < len) {
+                    const size_t go = ((size_t)(tok0 + m) * H + h) * D + c0 + col;
+                    st(dq + go, scale * Qt);
+                    st(dk + go, bt * Et + Yt);
+                    if (er) st(static_cast<TI*>(gd.derase) + go, kv * Et);   // db = K exp(G) .* E_bar
+                }
+                rowacc[ii] = fmaf(kv, Et, rowacc[ii]);
+                sF4[m * LD + col] = scale * qv * Qt + bt * kv * Et - kv * Yt;  // G_bar
             }
-            rowacc[ii] = fmaf(kv, Et, rowacc[ii]);
-            sF4[m * LD + col] = scale * qv * Qt + bt * kv * Et - kv * Yt;  // G_bar
+        }
+        if (GATE == 0) continue;
+        __syncthreads();
+        // state endpoints at the last valid token: lambda*rowsum(S.*S+bar) + sum_i F_i .* F_bar_i
+        if (tid < DC) {
+            const float glc = gl2[tid];
+            float e = exp2f(glc) * b.LAMB[ch * D + c0 + tid];
+            for (int i = 0; i < len; ++i)
+                e = fmaf(sK[i * LD + tid] * exp2f(glc - sG[i * LD + tid]), FB[(size_t)i * D + c0 + tid], e);
+            sF4[(len - 1) * LD + tid] += e;
+        }
+        __syncthreads();
+        if (GATE == 2) {
+            if (tid < DC) {
+                float acc = 0.f;
+                for (int r = len - 1; r >= 0; --r) {
+                    acc += sF4[r * LD + tid];
+                    dg[((size_t)(tok0 + r) * H + h) * D + c0 + tid] = acc;
+                }
+            }
+        } else {
+            // scalar gate: G_bar summed over the features of every block, per row
+            for (int r = warp; r < BT; r += NTHREADS / 32) {
+                float x = 0.f;
+                for (int col = lane; col < DC; col += 32) x += sF4[r * LD + col];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+                if (lane == 0) sRow[r] = cb == 0 ? x : sRow[r] + x;
+            }
         }
     }
     // dbeta = <k_i, gamma E_bar_i> + <v_i, P_i>; a warp owns whole rows (TNX = 32)
@@ -436,35 +511,8 @@ __device__ __forceinline__ void intra_chunk(int c, int h, const Shape& s, const 
         if (lane == 0 && m < len && !er)
             st(dbeta + (size_t)(tok0 + m) * H + h, x + b.DBW[ch * BT + m]);
     }
-    (void)warp;
-    __syncthreads();
-    if (GATE == 0) return;
-    // state endpoints at the last valid token: lambda*rowsum(S.*S+bar) + sum_i F_i .* F_bar_i
-    if (tid < D) {
-        const float glc = gl2[tid];
-        float e = exp2f(glc) * b.LAMB[ch * D + tid];
-        for (int i = 0; i < len; ++i)
-            e = fmaf(sK[i * LD + tid] * exp2f(glc - sG[i * LD + tid]), FB[(size_t)i * D + tid], e);
-        sF4[(len - 1) * LD + tid] += e;
-    }
-    __syncthreads();
-    if (GATE == 2) {
-        if (tid < D) {
-            float acc = 0.f;
-            for (int r = len - 1; r >= 0; --r) {
-                acc += sF4[r * LD + tid];
-                dg[((size_t)(tok0 + r) * H + h) * D + tid] = acc;
-            }
-        }
-    } else {
-        // scalar gate: sum features per row, then reverse cumsum over rows
-        for (int r = warp; r < BT; r += NTHREADS / 32) {
-            float x = 0.f;
-            for (int col = lane; col < D; col += 32) x += sF4[r * LD + col];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-            if (lane == 0) sRow[r] = x;
-        }
+    if (GATE == 1) {
+        // scalar gate: reverse cumsum of the row sums
         __syncthreads();
         if (tid == 0) {
             float acc = 0.f;
@@ -518,8 +566,8 @@ template <typename TI, typename IT, int D>
 cudaError_t run_dstate(const Shape& s, const void* dout, const void* v, const void* beta, Table t,
                        const IT* P, const IT* R, const IT* S, const IT* SB, const int32_t* list, Bwd b,
                        void* dv, cudaStream_t st, const Gdn2& gd = Gdn2{}) {
-    constexpr int LD = D + 1, LS = SL + 1;
-    constexpr size_t smem = sizeof(float) * (3 * BT * LD + 2 * D * LS);
+    constexpr int DC = D > 128 ? 128 : D, LD = DC + 1, LS = SL + 1;
+    constexpr size_t smem = sizeof(float) * (3 * BT * LD + 2 * DC * LS);
     auto kern = k_bwd_dstate<TI, IT, D>;
     cudaError_t e = set_smem_once<k_bwd_dstate<TI, IT, D>>(smem);
     if (e != cudaSuccess) return e;
@@ -533,8 +581,8 @@ template <typename TI, int D, int GATE>
 cudaError_t run_intra(const Shape& s, const void* q, const void* k, const void* beta, const float* g,
                       Table t, const int32_t* list, Bwd b, void* dq, void* dk, void* dbeta, float* dg,
                       cudaStream_t st, const Gdn2& gd) {
-    constexpr int LD = D + 1, LA = BT + 1;
-    constexpr size_t smem = sizeof(float) * (5 * BT * LD + 2 * BT * LA + 2 * BT + D);
+    constexpr int DC = D > 128 ? 128 : D, LD = DC + 1, LA = BT + 1;
+    constexpr size_t smem = sizeof(float) * (5 * BT * LD + 2 * BT * LA + 2 * BT + DC);
     auto kern = k_bwd_intra<TI, D, GATE>;
     cudaError_t e = set_smem_once<k_bwd_intra<TI, D, GATE>>(smem);
     if (e != cudaSuccess) return e;
@@ -559,6 +607,9 @@ cudaError_t run_intra_gate(int gate, const Shape& s, const void* q, const void* 
 
 cudaError_t launch_bwd_dstate(const Shape& s, int io_bf16, const void* dout, const void* v,
                               const void* beta, Table t, Fwd f, Bwd b, void* dv, cudaStream_t st, const Gdn2& gd) {
+    if (s.K == 256)
+        return io_bf16 ? run_dstate<__nv_bfloat16, float, 256>(s, dout, v, beta, t, b.P, f.R, f.SIN, b.SBP, nullptr, b, dv, st, gd)
+                       : run_dstate<float, float, 256>(s, dout, v, beta, t, b.P, f.R, f.SIN, b.SBP, nullptr, b, dv, st, gd);
     if (s.K == 128)
         return io_bf16 ? run_dstate<__nv_bfloat16, float, 128>(s, dout, v, beta, t, b.P, f.R, f.SIN, b.SBP, nullptr, b, dv, st, gd)
                        : run_dstate<float, float, 128>(s, dout, v, beta, t, b.P, f.R, f.SIN, b.SBP, nullptr, b, dv, st, gd);
@@ -570,6 +621,9 @@ cudaError_t launch_bwd_intra(const Shape& s, int io_bf16, int gate, const void* 
                              const void* beta, const float* g, Table t, Fwd f, Bwd b, void* dq,
                              void* dk, void* dbeta, float* dg, cudaStream_t st, const Gdn2& gd) {
     (void)f;
+    if (s.K == 256)
+        return io_bf16 ? run_intra_gate<__nv_bfloat16, 256>(gate, s, q, k, beta, g, t, nullptr, b, dq, dk, dbeta, dg, st, gd)
+                       : run_intra_gate<float, 256>(gate, s, q, k, beta, g, t, nullptr, b, dq, dk, dbeta, dg, st, gd);
     if (s.K == 128)
         return io_bf16 ? run_intra_gate<__nv_bfloat16, 128>(gate, s, q, k, beta, g, t, nullptr, b, dq, dk, dbeta, dg, st, gd)
                        : run_intra_gate<float, 128>(gate, s, q, k, beta, g, t, nullptr, b, dq, dk, dbeta, dg, st, gd);

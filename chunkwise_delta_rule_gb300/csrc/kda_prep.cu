@@ -19,15 +19,20 @@ namespace {
 
 // TCOUT: prepare only the chunks the tensor-core prep flagged as too wide for
 // one anchor, and write the tensor-core path's layouts (bf16 tile images).
+// Features are taken in column blocks of at most 128 (two passes at D = 256):
+// the a2 contractions over the key width add up block by block, everything
+// else is per feature.
 template <typename TI, int D, int GATE, bool TCOUT>
 __device__ __forceinline__ void prep_chunk(int c, int h, const Shape& s, const TI* __restrict__ q,
                                            const TI* __restrict__ k, const TI* __restrict__ v,
                                            const TI* __restrict__ beta, const float* __restrict__ g,
                                            const Table& t, const Fwd& f, const FwdTC& ft, const Gdn2& gd) {
-    constexpr int LD = D + 1;       // padded row stride of [BT x D] tiles
-    constexpr int LA = BT + 1;      // padded row stride of [BT x BT] tiles
+    constexpr int DC = D > 128 ? 128 : D;   // feature columns per pass
+    constexpr int NB = D / DC;              // passes
+    constexpr int LD = DC + 1;              // padded row stride of [BT x DC] tiles
+    constexpr int LA = BT + 1;              // padded row stride of [BT x BT] tiles
     extern __shared__ float smem[];
-    float* sK = smem;               // [BT][LD] keys (fp32)
+    float* sK = smem;               // [BT][LD] keys (fp32) of the column block
     float* sG = sK + BT * LD;       // [BT][LD] cumulative log2-decay
     float* sQ = sG + BT * LD;       // [BT][LD] queries, later beta*v
     float* sL = sQ + BT * LD;       // [2*BC][LD] row factors
@@ -35,6 +40,7 @@ __device__ __forceinline__ void prep_chunk(int c, int h, const Shape& s, const T
     float* sAkk = sR + BT * LD;     // [BT][LA]
     float* sAi = sAkk + BT * LA;    // [BT][LA]
     float* sBeta = sAi + BT * LA;   // [BT]
+    float* sAq = sBeta + BT;        // [BT][LA] C_q summed over the blocks (NB > 1 only)
 
     const int tid = threadIdx.x;
     const int n = t.chunk_len[c];
@@ -43,80 +49,98 @@ __device__ __forceinline__ void prep_chunk(int c, int h, const Shape& s, const T
     const int H = s.H;
     const size_t ch = (size_t)c * H + h;
 
-    // ---- load chunk rows (rows >= n are zero keys/queries and zero decay)
-    for (int idx = tid; idx < BT * D; idx += NTHREADS) {
-        const int r = idx / D, col = idx % D;
-        float kv = 0.f, qv = 0.f, gv = 0.f;
-        if (r < n) {
-            const size_t off = ((size_t)(tok0 + r) * H + h) * D + col;
-            kv = ld(k + off);
-            qv = ld(q + off);
-            if (GATE == 2) gv = g[off] * LOG2E;
-            if (GATE == 1) gv = g[(size_t)(tok0 + r) * H + h] * LOG2E;
-        }
-        sK[r * LD + col] = kv;
-        sQ[r * LD + col] = qv;
-        sG[r * LD + col] = gv;
-    }
     if (tid < BT) sBeta[tid] = (tid < n && !gd.erase) ? ld(beta + (size_t)(tok0 + tid) * H + h) : 0.f;
     // GatedDeltaNet-2: the erase vector takes beta's place on the key rows of E
     const TI* er = static_cast<const TI*>(gd.erase);
-    auto ebeta = [&](int r, int col) {
-        return er ? ((r < n) ? ld(er + ((size_t)(tok0 + r) * H + h) * D + col) : 0.f) : sBeta[r];
+    auto ebeta = [&](int r, int gcol) {
+        return er ? ((r < n) ? ld(er + ((size_t)(tok0 + r) * H + h) * D + gcol) : 0.f) : sBeta[r];
     };
-    __syncthreads();
-    // ---- a1: inclusive cumsum down each feature column (padding rows keep G[n-1])
-    if (tid < D) {
-        float acc = 0.f;
-        for (int r = 0; r < BT; ++r) {
-            acc += sG[r * LD + tid];
-            sG[r * LD + tid] = acc;
+    // ---- chunk rows of features c0 .. c0+DC-1 (rows >= n are zero keys/queries
+    // and zero decay), then a1: inclusive cumsum down each feature column
+    // (padding rows keep G[n-1])
+    auto load_block = [&](int c0) {
+        for (int idx = tid; idx < BT * DC; idx += NTHREADS) {
+            const int r = idx / DC, col = idx % DC;
+            float kv = 0.f, qv = 0.f, gv = 0.f;
+            if (r < n) {
+                const size_t off = ((size_t)(tok0 + r) * H + h) * D + c0 + col;
+                kv = ld(k + off);
+                qv = ld(q + off);
+                if (GATE == 2) gv = g[off] * LOG2E;
+                if (GATE == 1) gv = g[(size_t)(tok0 + r) * H + h] * LOG2E;
+            }
+            sK[r * LD + col] = kv;
+            sQ[r * LD + col] = qv;
+            sG[r * LD + col] = gv;
         }
-    }
-    __syncthreads();
+        __syncthreads();
+        if (tid < DC) {
+            float acc = 0.f;
+            for (int r = 0; r < BT; ++r) {
+                acc += sG[r * LD + tid];
+                sG[r * LD + tid] = acc;
+            }
+        }
+        __syncthreads();
+    };
 
     // ---- a2: Akk and Aqk, one 16-row sub-chunk of receiving rows at a time
     const float scale = s.scale;
     float* AQK = TCOUT ? nullptr : f.AQK + ch * BT * BT;
-    for (int b = 0; b < BT / BC; ++b) {
-        const int ra = b * BC + BC / 2;          // anchor row (padding rows repeat G[n-1])
-        const int ncol = (b + 1) * BC;           // columns j that can be <= i
-        for (int idx = tid; idx < 2 * BC * D; idx += NTHREADS) {
-            const int r = idx / D, col = idx % D;
-            const int i = b * BC + (r & (BC - 1));
-            const float e = exp2f(sG[i * LD + col] - sG[ra * LD + col]);
-            sL[r * LD + col] = (r < BC) ? ebeta(i, col) * sK[i * LD + col] * e : scale * sQ[i * LD + col] * e;
+    auto put_aqk = [&](int i, int j, float x) {
+        if (TCOUT) {
+            ft.AQK[ch * BT * BT + tile_el(BT, i, j)] = __float2bfloat16_rn(x);
+        } else {
+            AQK[i * BT + j] = x;
         }
-        for (int idx = tid; idx < ncol * D; idx += NTHREADS) {
-            const int j = idx / D, col = idx % D;
-            sR[j * LD + col] = sK[j * LD + col] * exp2f(sG[ra * LD + col] - sG[j * LD + col]);
-        }
-        __syncthreads();
-        float acc[4][2];
-        zero(acc);
-        tile_gemm<2 * BC, BT, 4, 2>(
-            acc, 0, D, [&](int m, int kk) { return sL[m * LD + kk]; },
-            [&](int kk, int nn) { return nn < ncol ? sR[nn * LD + kk] : 0.f; });
-        using TMp = TileMap<2 * BC, BT, 4, 2>;
-#pragma unroll
-        for (int ii = 0; ii < 4; ++ii) {
-#pragma unroll
-            for (int jj = 0; jj < 2; ++jj) {
-                const int r = TMp::row(ii), j = TMp::col(jj);
+    };
+    for (int cb = 0; cb < NB; ++cb) {
+        const int c0 = cb * DC;
+        if (cb > 0) __syncthreads();   // the previous block's tiles are no longer read
+        load_block(c0);
+        for (int b = 0; b < BT / BC; ++b) {
+            const int ra = b * BC + BC / 2;          // anchor row (padding rows repeat G[n-1])
+            const int ncol = (b + 1) * BC;           // columns j that can be <= i
+            for (int idx = tid; idx < 2 * BC * DC; idx += NTHREADS) {
+                const int r = idx / DC, col = idx % DC;
                 const int i = b * BC + (r & (BC - 1));
-                if (r < BC) {
-                    sAkk[i * LA + j] = (j < i && i < n) ? acc[ii][jj] : 0.f;
-                } else {
-                    const float x = (j <= i && i < n) ? acc[ii][jj] : 0.f;
-                    if (TCOUT) {
-                        ft.AQK[ch * BT * BT + tile_el(BT, i, j)] = __float2bfloat16_rn(x);
+                const float e = exp2f(sG[i * LD + col] - sG[ra * LD + col]);
+                sL[r * LD + col] = (r < BC) ? ebeta(i, c0 + col) * sK[i * LD + col] * e : scale * sQ[i * LD + col] * e;
+            }
+            for (int idx = tid; idx < ncol * DC; idx += NTHREADS) {
+                const int j = idx / DC, col = idx % DC;
+                sR[j * LD + col] = sK[j * LD + col] * exp2f(sG[ra * LD + col] - sG[j * LD + col]);
+            }
+            __syncthreads();
+            float acc[4][2];
+            zero(acc);
+            tile_gemm<2 * BC, BT, 4, 2>(
+                acc, 0, DC, [&](int m, int kk) { return sL[m * LD + kk]; },
+                [&](int kk, int nn) { return nn < ncol ? sR[nn * LD + kk] : 0.f; });
+            using TMp = TileMap<2 * BC, BT, 4, 2>;
+            // a thread owns the same (i, j) entries in every pass, so the block sums need no barrier
+#pragma unroll
+            for (int ii = 0; ii < 4; ++ii) {
+#pragma unroll
+                for (int jj = 0; jj < 2; ++jj) {
+                    const int r = TMp::row(ii), j = TMp::col(jj);
+                    const int i = b * BC + (r & (BC - 1));
+                    if (r < BC) {
+                        const float x = (j < i && i < n) ? acc[ii][jj] : 0.f;
+                        sAkk[i * LA + j] = cb == 0 ? x : sAkk[i * LA + j] + x;
                     } else {
-                        AQK[i * BT + j] = x;
+                        const float x = (j <= i && i < n) ? acc[ii][jj] : 0.f;
+                        if (NB == 1) {
+                            put_aqk(i, j, x);
+                        } else {
+                            sAq[i * LA + j] = cb == 0 ? x : sAq[i * LA + j] + x;
+                            if (cb == NB - 1) put_aqk(i, j, sAq[i * LA + j]);
+                        }
                     }
                 }
             }
+            __syncthreads();
         }
-        __syncthreads();
     }
 
     // ---- a3: A = (I + Akk)^-1 by forward substitution; 4 lanes per column
@@ -136,75 +160,81 @@ __device__ __forceinline__ void prep_chunk(int c, int h, const Shape& s, const T
         }
     }
     __syncthreads();
+    for (int idx = tid; idx < BT * BT; idx += NTHREADS) {
+        const float a = sAi[(idx / BT) * LA + idx % BT];
+        if (TCOUT) {
+            if (ft.AI) ft.AI[ch * BT * BT + tile_el(BT, idx / BT, idx % BT)] = __float2bfloat16_rn(a);
+        } else {
+            f.AINV[ch * BT * BT + idx] = a;
+        }
+    }
 
-    // ---- a4: Q_g, F (keys to chunk end), G at the last token
-    {
+    // ---- a4, per column block: Q_g, F (keys to chunk end), G at the last token,
+    // W = A E and U = A Z
+    constexpr int TN = DC / 32;
+    using TM8 = TileMap<BT, DC, 8, TN>;
+    for (int cb = 0; cb < NB; ++cb) {
+        const int c0 = cb * DC;
+        if (NB > 1) {
+            __syncthreads();   // the previous block's tiles are no longer read
+            load_block(c0);
+        }
         const float* gl = sG + (n - 1) * LD;
-        for (int idx = tid; idx < BT * D; idx += NTHREADS) {
-            const int r = idx / D, col = idx % D;
+        for (int idx = tid; idx < BT * DC; idx += NTHREADS) {
+            const int r = idx / DC, col = idx % DC;
             const float gr = sG[r * LD + col];
             const float qg = scale * sQ[r * LD + col] * exp2f(gr);
             const float kg = sK[r * LD + col] * exp2f(gl[col] - gr);
             if (TCOUT) {
-                ft.QG[ch * BT * D + tile_el(BT, r, col)] = __float2bfloat16_rn(qg);
-                ft.KG[ch * BT * D + tile_el(BT, r, col)] = __float2bfloat16_rn(kg);
+                ft.QG[ch * BT * D + tile_el(BT, r, c0 + col)] = __float2bfloat16_rn(qg);
+                ft.KG[ch * BT * D + tile_el(BT, r, c0 + col)] = __float2bfloat16_rn(kg);
             } else {
-                f.QG[ch * BT * D + idx] = qg;
-                f.KG[ch * BT * D + idx] = kg;
+                f.QG[ch * BT * D + (size_t)r * D + c0 + col] = qg;
+                f.KG[ch * BT * D + (size_t)r * D + c0 + col] = kg;
             }
         }
-        if (tid < D) (TCOUT ? ft.GL : f.GL)[ch * D + tid] = gl[tid];
-        for (int idx = tid; idx < BT * BT; idx += NTHREADS) {
-            const float a = sAi[(idx / BT) * LA + idx % BT];
-            if (TCOUT) {
-                if (ft.AI) ft.AI[ch * BT * BT + tile_el(BT, idx / BT, idx % BT)] = __float2bfloat16_rn(a);
-            } else {
-                f.AINV[ch * BT * BT + idx] = a;
-            }
+        if (tid < DC) (TCOUT ? ft.GL : f.GL)[ch * D + c0 + tid] = gl[tid];
+        // E = diag(beta) K exp(G) into sR; beta*v into sQ
+        for (int idx = tid; idx < BT * DC; idx += NTHREADS) {
+            const int r = idx / DC, col = idx % DC;
+            sR[r * LD + col] = ebeta(r, c0 + col) * sK[r * LD + col] * exp2f(sG[r * LD + col]);
         }
-    }
-    // E = diag(beta) K exp(G) into sR; beta*v into sQ
-    for (int idx = tid; idx < BT * D; idx += NTHREADS) {
-        const int r = idx / D, col = idx % D;
-        sR[r * LD + col] = ebeta(r, col) * sK[r * LD + col] * exp2f(sG[r * LD + col]);
-    }
-    __syncthreads();  // all reads of sQ (queries) are done
-    for (int idx = tid; idx < BT * D; idx += NTHREADS) {
-        const int r = idx / D, col = idx % D;
-        const size_t off = ((size_t)(tok0 + r) * H + h) * D + col;
-        const float wv = gd.write ? (r < n ? ld(static_cast<const TI*>(gd.write) + off) : 0.f) : sBeta[r];
-        sQ[r * LD + col] = (r < n) ? wv * ld(v + off) : 0.f;
-    }
-    __syncthreads();
-    constexpr int TN = D / 32;
-    using TM8 = TileMap<BT, D, 8, TN>;
-    {
-        float acc[8][TN];
-        zero(acc);
-        tile_gemm<BT, D, 8, TN>(acc, 0, BT, [&](int m, int kk) { return sAi[m * LA + kk]; },
-                                [&](int kk, int nn) { return sR[kk * LD + nn]; });
+        __syncthreads();  // all reads of sQ (queries) are done
+        for (int idx = tid; idx < BT * DC; idx += NTHREADS) {
+            const int r = idx / DC, col = idx % DC;
+            const size_t off = ((size_t)(tok0 + r) * H + h) * D + c0 + col;
+            const float wv = gd.write ? (r < n ? ld(static_cast<const TI*>(gd.write) + off) : 0.f) : sBeta[r];
+            sQ[r * LD + col] = (r < n) ? wv * ld(v + off) : 0.f;
+        }
+        __syncthreads();
+        {
+            float acc[8][TN];
+            zero(acc);
+            tile_gemm<BT, DC, 8, TN>(acc, 0, BT, [&](int m, int kk) { return sAi[m * LA + kk]; },
+                                     [&](int kk, int nn) { return sR[kk * LD + nn]; });
 #pragma unroll
-        for (int ii = 0; ii < 8; ++ii)
+            for (int ii = 0; ii < 8; ++ii)
 #pragma unroll
-            for (int jj = 0; jj < TN; ++jj) {
-                const int r = TM8::row(ii), cl = TM8::col(jj);
-                if (TCOUT) {
-                    ft.W[ch * BT * D + tile_el(BT, r, cl)] = __float2bfloat16_rn(acc[ii][jj]);
-                } else {
-                    f.W[ch * BT * D + r * D + cl] = acc[ii][jj];
+                for (int jj = 0; jj < TN; ++jj) {
+                    const int r = TM8::row(ii), cl = c0 + TM8::col(jj);
+                    if (TCOUT) {
+                        ft.W[ch * BT * D + tile_el(BT, r, cl)] = __float2bfloat16_rn(acc[ii][jj]);
+                    } else {
+                        f.W[ch * BT * D + r * D + cl] = acc[ii][jj];
+                    }
                 }
-            }
-    }
-    {
-        float acc[8][TN];
-        zero(acc);
-        tile_gemm<BT, D, 8, TN>(acc, 0, BT, [&](int m, int kk) { return sAi[m * LA + kk]; },
-                                [&](int kk, int nn) { return sQ[kk * LD + nn]; });
-        float* U = (TCOUT ? ft.U : f.U) + ch * BT * D;
+        }
+        {
+            float acc[8][TN];
+            zero(acc);
+            tile_gemm<BT, DC, 8, TN>(acc, 0, BT, [&](int m, int kk) { return sAi[m * LA + kk]; },
+                                     [&](int kk, int nn) { return sQ[kk * LD + nn]; });
+            float* U = (TCOUT ? ft.U : f.U) + ch * BT * D;
 #pragma unroll
-        for (int ii = 0; ii < 8; ++ii)
+            for (int ii = 0; ii < 8; ++ii)
 #pragma unroll
-            for (int jj = 0; jj < TN; ++jj) U[TM8::row(ii) * D + TM8::col(jj)] = acc[ii][jj];
+                for (int jj = 0; jj < TN; ++jj) U[TM8::row(ii) * D + c0 + TM8::col(jj)] = acc[ii][jj];
+        }
     }
 }
 
@@ -229,8 +259,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 template <typename TI, int D, int GATE, bool TCOUT>
 cudaError_t run(const Shape& s, const void* q, const void* k, const void* v, const void* beta,
                 const float* g, Table t, Fwd f, FwdTC ft, cudaStream_t st, const Gdn2& gd = Gdn2{}) {
-    constexpr int LD = D + 1, LA = BT + 1;
-    constexpr size_t smem = sizeof(float) * (3 * BT * LD + 2 * BC * LD + BT * LD + 2 * BT * LA + BT);
+    constexpr int DC = D > 128 ? 128 : D, LD = DC + 1, LA = BT + 1;
+    constexpr size_t smem = sizeof(float) * (4 * BT * LD + 2 * BC * LD + (D > DC ? 3 : 2) * BT * LA + BT);
     auto kern = k_prep<TI, D, GATE, TCOUT>;
     cudaError_t e = set_smem_once<k_prep<TI, D, GATE, TCOUT>>(smem);
     if (e != cudaSuccess) return e;
@@ -266,6 +296,10 @@ cudaError_t launch_prep_wide(const Shape& s, int gate, const void* q, const void
 cudaError_t launch_prep(const Shape& s, int io_bf16, int gate, const void* q, const void* k,
                         const void* v, const void* beta, const float* g, Table t, Fwd f,
                         cudaStream_t st, const Gdn2& gd) {
+    if (s.K == 256) {
+        return io_bf16 ? run_gate<__nv_bfloat16, 256>(gate, s, q, k, v, beta, g, t, f, st, gd)
+                       : run_gate<float, 256>(gate, s, q, k, v, beta, g, t, f, st, gd);
+    }
     if (s.K == 128) {
         return io_bf16 ? run_gate<__nv_bfloat16, 128>(gate, s, q, k, v, beta, g, t, f, st, gd)
                        : run_gate<float, 128>(gate, s, q, k, v, beta, g, t, f, st, gd);

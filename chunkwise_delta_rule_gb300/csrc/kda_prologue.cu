@@ -50,6 +50,10 @@ __device__ __forceinline__ void ldv(const float* p, float (&x)[4]) {
     const float4 v = *reinterpret_cast<const float4*>(p);
     x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
 }
+__device__ __forceinline__ void ldv(const float* p, float (&x)[8]) {
+    const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
 __device__ __forceinline__ void ldv(const float* p, float (&x)[2]) {
     const float2 v = *reinterpret_cast<const float2*>(p);
     x[0] = v.x; x[1] = v.y;
@@ -60,12 +64,26 @@ __device__ __forceinline__ void ldv(const __nv_bfloat16* p, float (&x)[4]) {
     const float2 a = __bfloat1622float2(h[0]), b = __bfloat1622float2(h[1]);
     x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
 }
+__device__ __forceinline__ void ldv(const __nv_bfloat16* p, float (&x)[8]) {
+    const uint4 v = *reinterpret_cast<const uint4*>(p);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 a = __bfloat1622float2(h[i]);
+        x[2 * i] = a.x;
+        x[2 * i + 1] = a.y;
+    }
+}
 __device__ __forceinline__ void ldv(const __nv_bfloat16* p, float (&x)[2]) {
     const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(p);
     const float2 a = __bfloat1622float2(v);
     x[0] = a.x; x[1] = a.y;
 }
 __device__ __forceinline__ void stv(float* p, const float (&x)[4]) { *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]); }
+__device__ __forceinline__ void stv(float* p, const float (&x)[8]) {
+    reinterpret_cast<float4*>(p)[0] = make_float4(x[0], x[1], x[2], x[3]);
+    reinterpret_cast<float4*>(p)[1] = make_float4(x[4], x[5], x[6], x[7]);
+}
 __device__ __forceinline__ void stv(float* p, const float (&x)[2]) { *reinterpret_cast<float2*>(p) = make_float2(x[0], x[1]); }
 __device__ __forceinline__ void stv(__nv_bfloat16* p, const float (&x)[4]) {
     uint2 v;
@@ -73,6 +91,13 @@ __device__ __forceinline__ void stv(__nv_bfloat16* p, const float (&x)[4]) {
     h[0] = __floats2bfloat162_rn(x[0], x[1]);
     h[1] = __floats2bfloat162_rn(x[2], x[3]);
     *reinterpret_cast<uint2*>(p) = v;
+}
+__device__ __forceinline__ void stv(__nv_bfloat16* p, const float (&x)[8]) {
+    uint4 v;
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
+    *reinterpret_cast<uint4*>(p) = v;
 }
 __device__ __forceinline__ void stv(__nv_bfloat16* p, const float (&x)[2]) {
     *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(x[0], x[1]);
@@ -277,18 +302,22 @@ cudaError_t run_epilogue_k(const Shape& s, int gate, const EpilogueArgs& a, cuda
 int prologue_blocks(int Ttot) { return (Ttot + ETB - 1) / ETB; }
 
 cudaError_t launch_prologue(const Shape& s, int bf16, int gate, const PrologueArgs& a, cudaStream_t st) {
-    if (s.K != 64 && s.K != 128) return cudaErrorInvalidValue;
-    if (bf16) return s.K == 128 ? run_prologue_k<__nv_bfloat16, 128>(s, gate, a, st)
-                                : run_prologue_k<__nv_bfloat16, 64>(s, gate, a, st);
-    return s.K == 128 ? run_prologue_k<float, 128>(s, gate, a, st) : run_prologue_k<float, 64>(s, gate, a, st);
+    switch (s.K) {
+        case 64: return bf16 ? run_prologue_k<__nv_bfloat16, 64>(s, gate, a, st) : run_prologue_k<float, 64>(s, gate, a, st);
+        case 128: return bf16 ? run_prologue_k<__nv_bfloat16, 128>(s, gate, a, st) : run_prologue_k<float, 128>(s, gate, a, st);
+        case 256: return bf16 ? run_prologue_k<__nv_bfloat16, 256>(s, gate, a, st) : run_prologue_k<float, 256>(s, gate, a, st);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 cudaError_t launch_epilogue(const Shape& s, int bf16, int gate, const EpilogueArgs& a, cudaStream_t st) {
-    if (s.K != 64 && s.K != 128) return cudaErrorInvalidValue;
-    cudaError_t e = bf16 ? (s.K == 128 ? run_epilogue_k<__nv_bfloat16, 128>(s, gate, a, st)
-                                       : run_epilogue_k<__nv_bfloat16, 64>(s, gate, a, st))
-                         : (s.K == 128 ? run_epilogue_k<float, 128>(s, gate, a, st)
-                                       : run_epilogue_k<float, 64>(s, gate, a, st));
+    cudaError_t e;
+    switch (s.K) {
+        case 64: e = bf16 ? run_epilogue_k<__nv_bfloat16, 64>(s, gate, a, st) : run_epilogue_k<float, 64>(s, gate, a, st); break;
+        case 128: e = bf16 ? run_epilogue_k<__nv_bfloat16, 128>(s, gate, a, st) : run_epilogue_k<float, 128>(s, gate, a, st); break;
+        case 256: e = bf16 ? run_epilogue_k<__nv_bfloat16, 256>(s, gate, a, st) : run_epilogue_k<float, 256>(s, gate, a, st); break;
+        default: return cudaErrorInvalidValue;
+    }
     if (e != cudaSuccess || gate == 0 || !a.A_log) return e;
     const int NC = gate == 2 ? s.K : 1;
     const int n = s.H * NC;

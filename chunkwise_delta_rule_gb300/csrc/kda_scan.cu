@@ -257,6 +257,9 @@ cudaError_t run_bwd(const Shape& s, const void* dout, const float* dht, Table t,
 
 cudaError_t launch_fwd_scan(const Shape& s, int io_bf16, int mode, const float* h0, Table t,
                             Fwd f, void* o, float* ht, cudaStream_t st) {
+    if (s.K == 256)
+        return io_bf16 ? run_fwd_mode<__nv_bfloat16, 256>(mode, s, h0, t, f, o, ht, st)
+                       : run_fwd_mode<float, 256>(mode, s, h0, t, f, o, ht, st);
     if (s.K == 128)
         return io_bf16 ? run_fwd_mode<__nv_bfloat16, 128>(mode, s, h0, t, f, o, ht, st)
                        : run_fwd_mode<float, 128>(mode, s, h0, t, f, o, ht, st);
@@ -266,6 +269,9 @@ cudaError_t launch_fwd_scan(const Shape& s, int io_bf16, int mode, const float* 
 
 cudaError_t launch_bwd_scan(const Shape& s, int io_bf16, const void* dout, const float* dht,
                             Table t, Fwd f, Bwd b, float* dh0, cudaStream_t st) {
+    if (s.K == 256)
+        return io_bf16 ? run_bwd<__nv_bfloat16, 256>(s, dout, dht, t, f, b, dh0, st)
+                       : run_bwd<float, 256>(s, dout, dht, t, f, b, dh0, st);
     if (s.K == 128)
         return io_bf16 ? run_bwd<__nv_bfloat16, 128>(s, dout, dht, t, f, b, dh0, st)
                        : run_bwd<float, 128>(s, dout, dht, t, f, b, dh0, st);

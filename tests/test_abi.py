@@ -93,8 +93,8 @@ def test_workspace_size_arithmetic():
 
 
 @pytest.mark.parametrize("kw,status", [
-    (dict(K=192, V=192), 2),
-    (dict(K=160, V=128), 2),
+    (dict(K=257, V=192), 2),
+    (dict(K=320, V=128), 2),
     (dict(B=0), 1),
     (dict(gate=7), 1),
     (dict(io=5), 1),
@@ -214,6 +214,20 @@ def test_unequal_widths_pad_to_the_working_width():
     assert _ws(small, 0) > 0
     z = ctypes.c_void_p(0x3000)
     assert lib.kda_recurrent_fwd(ctypes.byref(p), z, None, None, None) == 2
+    # key widths above 128 run at 256 (the value side too)
+    wide = _prob(K=192, V=160)
+    work = _prob(K=256, V=256)
+    D = 256
+    pad_f = 3 * up(2 * T * H * D) + up(4 * T * H * D) + up(2 * T * H * D) + up(4 * 2 * H * D * D)
+    assert _ws(wide, 0) == _ws(work, 0) + pad_f
+    pad_b = pad_f + up(2 * T * H * D) + up(4 * 2 * H * D * D) + 3 * up(2 * T * H * D) + up(4 * T * H * D) \
+        + up(4 * 2 * H * D * D)
+    assert _ws(wide, 1) == _ws(work, 1) + pad_b
+    # K = V = 256 is a working width itself: its workspace is the chunk pipeline's (fp32 intermediates)
+    NC, chd = 2 * 3, 2 * 3 * 3
+    table = 2 * up(4 * NC) + up(4 * 3) + 2 * up(4 * 2) + up(4)
+    fcore = 4 * up(4 * chd * 64 * D) + 2 * up(4 * chd * 64 * 64) + up(4 * chd * D)
+    assert _ws(work, 0) == table + fcore
 
 
 def test_wide_values_run_as_value_blocks():
@@ -241,8 +255,13 @@ def test_wide_values_run_as_value_blocks():
     rows = up(2 * T * Hv * 202)
     split_f = 2 * rows + up(2 * T * Hv * NB) + up(4 * T * Hv * NB) + up(4 * 2 * Hv * K * 202)
     assert _ws(odd, 0) == _ws(inner, 0) + split_f
-    # limits: key width above 128; value width above 4096; value heads x blocks above 65535
-    for kw, fld in ((dict(K=192), None), (dict(V=4097), None), (dict(H=30000, V=384), None)):
+    # above K = 128 the value blocks are 256 wide: K = 192, V = 512 is two blocks of 256
+    kb = _prob(K=192, V=512)
+    inner = _set(_prob(K=192, V=256), HV=6)
+    split_f = up(2 * T * Hv * NB) + up(4 * T * Hv * NB * 192) + up(4 * 2 * Hv * 192 * 512)
+    assert _ws(kb, 0) == _ws(inner, 0) + split_f
+    # limits: key width above 256; value width above 4096; value heads x blocks above 65535
+    for kw, fld in ((dict(K=257), None), (dict(V=4097), None), (dict(H=30000, V=384), None)):
         q = _prob(**kw)
         assert lib.kda_chunk_fwd(ctypes.byref(q), z, None, None, None, 0, None) == 2
         assert _ws(q, 0) == 0

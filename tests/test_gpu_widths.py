@@ -1,8 +1,9 @@
 """GPU parity at key and value widths other than K = V = 64 or 128 (served
-zero-padded to the working width and cropped back; value widths above 128 as
-value blocks, each a value head of its own), alone and together with grouped
-value heads, the GatedDeltaNet-2 vectors and the prologue, against the FP64
-oracle at the true widths."""
+zero-padded to the working width, 64, 128 or 256, and cropped back; value
+widths above the value-block width, 128 or 256 when K > 128, as value blocks,
+each a value head of its own), alone and together with grouped value heads,
+the GatedDeltaNet-2 vectors and the prologue, against the FP64 oracle at the
+true widths."""
 
 import numpy as np
 import pytest
@@ -51,7 +52,7 @@ def run_both(case, G=1, gdn2=False, prologue=False):
     if gdn2:
         extra.update(erase=b.cuda(), write=w.cuda())
     prob = kda.make_problem(qk[0].cuda(), qk[1].cuda(), c.v, c.g, None if gdn2 else c.beta, gate=case.gate,
-                            scale=case.scale, initial_state=c.h0, **extra)
+                            scale=case.scale, initial_state=c.h0, cu_seqlens=c.cu_seqlens, **extra)
     o, ht, sv = kda.kda_chunk_fwd(prob)
     r = kda.kda_chunk_bwd(prob, c.do, c.dht, saved=sv)
     torch.cuda.synchronize()
@@ -117,6 +118,61 @@ def test_wide_values_saved_equals_recomputed():
     out = []
     for policy in (0, 1):
         p = kda.make_problem(c.q, c.k, c.v, c.g, c.beta, gate="channel", scale=case.scale, initial_state=c.h0,
+                             save_policy=policy)
+        o, ht, sv = kda.kda_chunk_fwd(p)
+        out.append((o, ht) + tuple(kda.kda_chunk_bwd(p, c.do, c.dht, saved=sv)))
+    torch.cuda.synchronize()
+    for a, b in zip(*out):
+        if a is not None:
+            assert torch.equal(a, b)
+
+
+# key widths above 128: every key- and value-side tensor runs zero-padded to 256 (K = V = 256 as
+# is) on the fp32 CUDA-core kernels, which take the features in blocks of 128
+@pytest.mark.parametrize("gate", ["channel", "scalar", "none"])
+@pytest.mark.parametrize("K,V", [(192, 160), (256, 256), (160, 64)])
+def test_wide_keys_match_oracle(gate, K, V):
+    case = width_case("bf16", gate, 2, 100, 2, K, V, 106)
+    got, ref = run_both(case)
+    compare(case, got, ref, 1, TOL["bf16"])
+
+
+@pytest.mark.parametrize("gate,K,V", [("channel", 256, 256), ("scalar", 200, 136)])
+def test_wide_keys_fp32_packed(gate, K, V):
+    case = make_case(io="fp32", gate=gate, B=1, H=2, K=K, V=V, seed=107, lengths=[1, 64, 130, 3, 70])
+    got, ref = run_both(case)
+    compare(case, got, ref, 1, TOL["fp32"])
+
+
+def test_wide_keys_strong_decay():
+    """g around -4 at K = 256: the in-chunk gate range passes the centering
+    threshold, so the consumer's 16-token anchored path runs in both feature
+    blocks."""
+    case = make_case(io="bf16", gate="channel", B=1, T=200, H=2, K=256, V=256, seed=108, g_shift=-4.0,
+                     g_min=-8.0)
+    G = torch.cumsum(case.g.double(), dim=1) / np.log(2.0)
+    assert float((G[:, :64].max(dim=1).values - G[:, :64].min(dim=1).values).max()) > 80
+    got, ref = run_both(case)
+    compare(case, got, ref, 1, TOL["bf16"])
+
+
+def test_wide_keys_with_value_blocks_grouped_heads_gdn2_and_prologue():
+    # K = 192, V = 512: two value blocks of 256
+    case = width_case("bf16", "channel", 1, 90, 2, 192, 512, 109)
+    got, ref = run_both(case)
+    compare(case, got, ref, 1, TOL["bf16"])
+    case = width_case("bf16", "channel", 1, 90, 4, 192, 160, 110)
+    got, ref = run_both(case, G=2, gdn2=True, prologue=True)
+    compare(case, got, ref, 2, TOL["bf16"])
+
+
+def test_wide_keys_saved_equals_recomputed():
+    import chunkwise_delta_rule_gb300 as kda
+    case = width_case("bf16", "scalar", 1, 150, 2, 256, 256, 111)
+    c = case.to("cuda")
+    out = []
+    for policy in (0, 1):
+        p = kda.make_problem(c.q, c.k, c.v, c.g, c.beta, gate="scalar", scale=case.scale, initial_state=c.h0,
                              save_policy=policy)
         o, ht, sv = kda.kda_chunk_fwd(p)
         out.append((o, ht) + tuple(kda.kda_chunk_bwd(p, c.do, c.dht, saved=sv)))
