@@ -62,14 +62,14 @@ __device__ __forceinline__ void dstate_chunk(int c, int h, const Shape& s, const
     const IT* R = Rin + ch * BT * D;
     // dO, P and R of value columns v0 .. v0+DC-1
     auto load_block = [&](int v0) {
-        for (int idx = tid; idx < BT * DC; idx += NTHREADS) {
-            const int r = idx / DC, col = v0 + idx % DC;
-            const int e = IMG ? tile_el(BT, r, col) : r * D + col;
-            const int o = r * LD + idx % DC;
-            sO[o] = (r < len) ? ld(dout + ((size_t)(tok0 + r) * H + h) * D + col) : 0.f;
-            sP[o] = ld(P + e);
-            sR[o] = ld(R + e);
-        }
+        auto e = [&](int r, int col) { return IMG ? tile_el(BT, r, v0 + col) : r * D + v0 + col; };
+        tile_copy<BT, DC>(
+            [&](int r, int col) { return (r < len) ? ldg(dout + ((size_t)(tok0 + r) * H + h) * D + v0 + col) : 0.f; },
+            [&](int r, int col, float x) { sO[r * LD + col] = x; });
+        tile_copy<BT, DC>([&](int r, int col) { return ldg(P + e(r, col)); },
+                          [&](int r, int col, float x) { sP[r * LD + col] = x; });
+        tile_copy<BT, DC>([&](int r, int col) { return ldg(R + e(r, col)); },
+                          [&](int r, int col, float x) { sR[r * LD + col] = x; });
     };
     // ---- value-width contractions, value block by value block:
     // dv = beta P and <v_i, P_i>, one warp per row (GatedDeltaNet-2: dv = w .* P, dw = v .* P);
@@ -157,12 +157,13 @@ __device__ __forceinline__ void dstate_chunk(int c, int h, const Shape& s, const
             }
             for (int vs = 0; vs < DC; vs += SL) {
                 __syncthreads();
-                for (int idx = tid; idx < DC * SL; idx += NTHREADS) {
-                    const int r = k0 + idx / SL, cc = v0 + vs + idx % SL;
-                    const size_t e = IMG ? (size_t)tile_el(D, r, cc) : (size_t)r * D + cc;
-                    sS[(idx / SL) * LS + idx % SL] = ld(SIN + e);
-                    sT[(idx / SL) * LS + idx % SL] = ld(SBP + e);
-                }
+                auto e = [&](int r, int cc) {
+                    return IMG ? (size_t)tile_el(D, k0 + r, v0 + vs + cc) : (size_t)(k0 + r) * D + v0 + vs + cc;
+                };
+                tile_copy<DC, SL>([&](int r, int cc) { return ldg(SIN + e(r, cc)); },
+                                  [&](int r, int cc, float x) { sS[r * LS + cc] = x; });
+                tile_copy<DC, SL>([&](int r, int cc) { return ldg(SBP + e(r, cc)); },
+                                  [&](int r, int cc, float x) { sT[r * LS + cc] = x; });
                 __syncthreads();
                 tile_gemm<BT, DC, 8, TN>(aQ, 0, SL, [&](int m, int kk) { return sO[m * LD + vs + kk]; },
                                          [&](int kk, int nn) { return sS[nn * LS + kk]; });
@@ -225,12 +226,12 @@ __device__ __forceinline__ void intra_chunk(int c, int h, const Shape& s, const 
     {
         const float* DM = b.DM + ch * BT * BT;
         const float* HQ = b.HQ + ch * BT * BT;
-        for (int idx = tid; idx < BT * BT; idx += NTHREADS) {
-            sDM[(idx / BT) * LA + idx % BT] = DM[idx];
-            sHQ[(idx / BT) * LA + idx % BT] = HQ[idx];
-        }
+        tile_copy<BT, BT>([&](int r, int cc) { return ldg(DM + r * BT + cc); },
+                          [&](int r, int cc, float x) { sDM[r * LA + cc] = x; });
+        tile_copy<BT, BT>([&](int r, int cc) { return ldg(HQ + r * BT + cc); },
+                          [&](int r, int cc, float x) { sHQ[r * LA + cc] = x; });
     }
-    if (tid < BT) sBeta[tid] = (tid < len && !gd.erase) ? ld(beta + (size_t)(tok0 + tid) * H + h) : 0.f;
+    if (tid < BT) sBeta[tid] = (tid < len && !gd.erase) ? ldg(beta + (size_t)(tok0 + tid) * H + h) : 0.f;
     // GatedDeltaNet-2: the erase vector takes beta's place on the key side (E = b .* K exp(G))
     const TI* er = static_cast<const TI*>(gd.erase);
     auto ebeta = [&](int r, int gcol) {
@@ -248,20 +249,17 @@ __device__ __forceinline__ void intra_chunk(int c, int h, const Shape& s, const 
     for (int cb = 0; cb < NB; ++cb) {
         const int c0 = cb * DC;
         if (cb > 0) __syncthreads();   // the previous block's tiles are no longer read
-        for (int idx = tid; idx < BT * DC; idx += NTHREADS) {
-            const int r = idx / DC, col = idx % DC;
-            float kv = 0.f, qv = 0.f, gv = 0.f;
-            if (r < len) {
-                const size_t off = ((size_t)(tok0 + r) * H + h) * D + c0 + col;
-                kv = ld(k + off);
-                qv = ld(q + off);
-                if (GATE == 2) gv = g[off] * LOG2E;
-                if (GATE == 1) gv = g[(size_t)(tok0 + r) * H + h] * LOG2E;
-            }
-            sK[r * LD + col] = kv;
-            sQ[r * LD + col] = qv;
-            sG[r * LD + col] = gv;
-        }
+        auto off = [&](int r, int col) { return ((size_t)(tok0 + r) * H + h) * D + c0 + col; };
+        tile_copy<BT, DC>([&](int r, int col) { return r < len ? ldg(k + off(r, col)) : 0.f; },
+                          [&](int r, int col, float x) { sK[r * LD + col] = x; });
+        tile_copy<BT, DC>([&](int r, int col) { return r < len ? ldg(q + off(r, col)) : 0.f; },
+                          [&](int r, int col, float x) { sQ[r * LD + col] = x; });
+        tile_copy<BT, DC>(
+            [&](int r, int col) {
+                if (GATE == 0 || r >= len) return 0.f;
+                return (GATE == 2 ? ldg(g + off(r, col)) : ldg(g + (size_t)(tok0 + r) * H + h)) * LOG2E;
+            },
+            [&](int r, int col, float x) { sG[r * LD + col] = x; });
         __syncthreads();
         int wide_col = 0;
         if (tid < DC) {
@@ -278,8 +276,14 @@ __device__ __forceinline__ void intra_chunk(int c, int h, const Shape& s, const 
             sC[tid] = (GATE == 2) ? 0.5f * (hi + lo) : 0.f;   // midpoint center
             wide_col = (GATE == 2) && (hi - lo > CENTER_RANGE_LOG2);
         }
-        // gate-range dispatch: one wide feature sends the block to the sub-chunk path
-        const bool wide = __syncthreads_or(wide_col) != 0;
+        // gate-range dispatch: one wide feature sends the block to the sub-chunk path (per-channel
+        // gates only, so that the other instantiations drop that path at compile time)
+        bool wide = false;
+        if (GATE == 2) {
+            wide = __syncthreads_or(wide_col) != 0;
+        } else {
+            __syncthreads();
+        }
         if (GATE == 1 && cb == 0) {
             // scalar gate: fold the exact pairwise decay exp(G_i - G_j) (<= 1) into D and H_q
             for (int idx = tid; idx < BT * BT; idx += NTHREADS) {

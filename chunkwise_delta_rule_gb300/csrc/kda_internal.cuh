@@ -112,6 +112,35 @@ __device__ __forceinline__ float ld(const float* p) { return *p; }
 __device__ __forceinline__ float ld(const __nv_bfloat16* p) { return __bfloat162float(*p); }
 __device__ __forceinline__ void st(float* p, float x) { *p = x; }
 __device__ __forceinline__ void st(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
+// read-only loads (data no launch writes while it runs)
+__device__ __forceinline__ float ldg(const float* p) { return __ldg(p); }
+__device__ __forceinline__ float ldg(const __nv_bfloat16* p) { return __bfloat162float(__ldg(p)); }
+
+// Fills an [R][C] tile: v = get(r, c), then put(r, c, v), over the CTA's threads (consecutive
+// threads take consecutive c, so the loads coalesce). The loads of a batch of B elements per
+// thread are all issued before any of their stores, so a tile costs about IT / B memory latencies
+// instead of IT (IT = R C / NTHREADS elements per thread).
+template <int R, int C, int B = 16, class G, class P>
+__device__ __forceinline__ void tile_copy(G get, P put) {
+    static_assert((R * C) % NTHREADS == 0, "tile must split evenly over the threads");
+    constexpr int IT = R * C / NTHREADS;
+    constexpr int BB = IT < B ? IT : B;
+    static_assert(IT % BB == 0, "batch must divide the per-thread count");
+#pragma unroll 1
+    for (int i0 = 0; i0 < IT; i0 += BB) {
+        float v[BB];
+#pragma unroll
+        for (int i = 0; i < BB; ++i) {
+            const int idx = (int)threadIdx.x + (i0 + i) * NTHREADS;
+            v[i] = get(idx / C, idx % C);
+        }
+#pragma unroll
+        for (int i = 0; i < BB; ++i) {
+            const int idx = (int)threadIdx.x + (i0 + i) * NTHREADS;
+            put(idx / C, idx % C, v[i]);
+        }
+    }
+}
 
 // ------------------------------------------------------- CUDA-core tile GEMM
 // acc[i][j] += sum_{kk < Kdim} A(m_i, kk) * B(kk, n_j) over the calling

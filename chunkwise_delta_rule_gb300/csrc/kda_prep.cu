@@ -49,7 +49,7 @@ __device__ __forceinline__ void prep_chunk(int c, int h, const Shape& s, const T
     const int H = s.H;
     const size_t ch = (size_t)c * H + h;
 
-    if (tid < BT) sBeta[tid] = (tid < n && !gd.erase) ? ld(beta + (size_t)(tok0 + tid) * H + h) : 0.f;
+    if (tid < BT) sBeta[tid] = (tid < n && !gd.erase) ? ldg(beta + (size_t)(tok0 + tid) * H + h) : 0.f;
     // GatedDeltaNet-2: the erase vector takes beta's place on the key rows of E
     const TI* er = static_cast<const TI*>(gd.erase);
     auto ebeta = [&](int r, int gcol) {
@@ -59,20 +59,17 @@ __device__ __forceinline__ void prep_chunk(int c, int h, const Shape& s, const T
     // and zero decay), then a1: inclusive cumsum down each feature column
     // (padding rows keep G[n-1])
     auto load_block = [&](int c0) {
-        for (int idx = tid; idx < BT * DC; idx += NTHREADS) {
-            const int r = idx / DC, col = idx % DC;
-            float kv = 0.f, qv = 0.f, gv = 0.f;
-            if (r < n) {
-                const size_t off = ((size_t)(tok0 + r) * H + h) * D + c0 + col;
-                kv = ld(k + off);
-                qv = ld(q + off);
-                if (GATE == 2) gv = g[off] * LOG2E;
-                if (GATE == 1) gv = g[(size_t)(tok0 + r) * H + h] * LOG2E;
-            }
-            sK[r * LD + col] = kv;
-            sQ[r * LD + col] = qv;
-            sG[r * LD + col] = gv;
-        }
+        auto off = [&](int r, int col) { return ((size_t)(tok0 + r) * H + h) * D + c0 + col; };
+        tile_copy<BT, DC>([&](int r, int col) { return r < n ? ldg(k + off(r, col)) : 0.f; },
+                          [&](int r, int col, float x) { sK[r * LD + col] = x; });
+        tile_copy<BT, DC>([&](int r, int col) { return r < n ? ldg(q + off(r, col)) : 0.f; },
+                          [&](int r, int col, float x) { sQ[r * LD + col] = x; });
+        tile_copy<BT, DC>(
+            [&](int r, int col) {
+                if (GATE == 0 || r >= n) return 0.f;
+                return (GATE == 2 ? ldg(g + off(r, col)) : ldg(g + (size_t)(tok0 + r) * H + h)) * LOG2E;
+            },
+            [&](int r, int col, float x) { sG[r * LD + col] = x; });
         __syncthreads();
         if (tid < DC) {
             float acc = 0.f;
@@ -200,12 +197,14 @@ __device__ __forceinline__ void prep_chunk(int c, int h, const Shape& s, const T
             sR[r * LD + col] = ebeta(r, c0 + col) * sK[r * LD + col] * exp2f(sG[r * LD + col]);
         }
         __syncthreads();  // all reads of sQ (queries) are done
-        for (int idx = tid; idx < BT * DC; idx += NTHREADS) {
-            const int r = idx / DC, col = idx % DC;
-            const size_t off = ((size_t)(tok0 + r) * H + h) * D + c0 + col;
-            const float wv = gd.write ? (r < n ? ld(static_cast<const TI*>(gd.write) + off) : 0.f) : sBeta[r];
-            sQ[r * LD + col] = (r < n) ? wv * ld(v + off) : 0.f;
-        }
+        tile_copy<BT, DC>(
+            [&](int r, int col) {
+                if (r >= n) return 0.f;
+                const size_t off = ((size_t)(tok0 + r) * H + h) * D + c0 + col;
+                const float wv = gd.write ? ldg(static_cast<const TI*>(gd.write) + off) : sBeta[r];
+                return wv * ldg(v + off);
+            },
+            [&](int r, int col, float x) { sQ[r * LD + col] = x; });
         __syncthreads();
         {
             float acc[8][TN];

@@ -32,10 +32,8 @@ __global__ void __launch_bounds__(NTHREADS)
     const int nseq = blockIdx.x, h = blockIdx.y, v0 = blockIdx.z * VT, tid = threadIdx.x;
     const int H = s.H;
     const size_t st_off = ((size_t)nseq * H + h) * D * D;
-    for (int idx = tid; idx < D * VT; idx += NTHREADS) {
-        const int r = idx / VT, cc = idx % VT;
-        sS[r * LV + cc] = h0 ? h0[st_off + (size_t)r * D + v0 + cc] : 0.f;
-    }
+    tile_copy<D, VT>([&](int r, int cc) { return h0 ? ldg(h0 + st_off + (size_t)r * D + v0 + cc) : 0.f; },
+                     [&](int r, int cc, float x) { sS[r * LV + cc] = x; });
     const int c0 = t.seq_chunk0[nseq], c1 = t.seq_chunk0[nseq + 1];
     using TR = TileMap<BT, VT, 8, 1>;
     using TS = TileMap<D, VT, D / 8, 1>;
@@ -44,12 +42,11 @@ __global__ void __launch_bounds__(NTHREADS)
         const int len = t.chunk_len[c], tok0 = t.chunk_tok0[c];
         const float* W = f.W + ch * BT * D;
         const float* U = f.U + ch * BT * D;
-        for (int idx = tid; idx < BT * D; idx += NTHREADS) sM[(idx / D) * LD + idx % D] = W[idx];
-        for (int idx = tid; idx < BT * VT; idx += NTHREADS) {
-            const int r = idx / VT, cc = idx % VT;
-            sR[r * LV + cc] = U[(size_t)r * D + v0 + cc];
-        }
-        if (tid < D) sLam[tid] = exp2f(f.GL[ch * D + tid]);
+        tile_copy<BT, D>([&](int r, int cc) { return ldg(W + r * D + cc); },
+                         [&](int r, int cc, float x) { sM[r * LD + cc] = x; });
+        tile_copy<BT, VT>([&](int r, int cc) { return ldg(U + (size_t)r * D + v0 + cc); },
+                          [&](int r, int cc, float x) { sR[r * LV + cc] = x; });
+        if (tid < D) sLam[tid] = exp2f(ldg(f.GL + ch * D + tid));
         __syncthreads();
         // R = U - W S
         {
@@ -76,8 +73,10 @@ __global__ void __launch_bounds__(NTHREADS)
         if (MODE & 1) {
             const float* QG = f.QG + ch * BT * D;
             const float* AQK = f.AQK + ch * BT * BT;
-            for (int idx = tid; idx < BT * D; idx += NTHREADS) sM[(idx / D) * LD + idx % D] = QG[idx];
-            for (int idx = tid; idx < BT * BT; idx += NTHREADS) sA[(idx / BT) * LA + idx % BT] = AQK[idx];
+            tile_copy<BT, D>([&](int r, int cc) { return ldg(QG + r * D + cc); },
+                             [&](int r, int cc, float x) { sM[r * LD + cc] = x; });
+            tile_copy<BT, BT>([&](int r, int cc) { return ldg(AQK + r * BT + cc); },
+                              [&](int r, int cc, float x) { sA[r * LA + cc] = x; });
             __syncthreads();
             float acc[8][1];
             zero(acc);
@@ -94,7 +93,8 @@ __global__ void __launch_bounds__(NTHREADS)
         }
         {
             const float* KG = f.KG + ch * BT * D;
-            for (int idx = tid; idx < BT * D; idx += NTHREADS) sM[(idx / D) * LD + idx % D] = KG[idx];
+            tile_copy<BT, D>([&](int r, int cc) { return ldg(KG + r * D + cc); },
+                             [&](int r, int cc, float x) { sM[r * LD + cc] = x; });
             __syncthreads();
             float acc[D / 8][1];
             zero(acc);
@@ -133,10 +133,8 @@ __global__ void __launch_bounds__(NTHREADS)
     const int nseq = blockIdx.x, h = blockIdx.y, v0 = blockIdx.z * VT, tid = threadIdx.x;
     const int H = s.H;
     const size_t st_off = ((size_t)nseq * H + h) * D * D;
-    for (int idx = tid; idx < D * VT; idx += NTHREADS) {
-        const int r = idx / VT, cc = idx % VT;
-        sSb[r * LV + cc] = dht ? dht[st_off + (size_t)r * D + v0 + cc] : 0.f;
-    }
+    tile_copy<D, VT>([&](int r, int cc) { return dht ? ldg(dht + st_off + (size_t)r * D + v0 + cc) : 0.f; },
+                     [&](int r, int cc, float x) { sSb[r * LV + cc] = x; });
     const int c0 = t.seq_chunk0[nseq], c1 = t.seq_chunk0[nseq + 1];
     using TR = TileMap<BT, VT, 8, 1>;
     using TS = TileMap<D, VT, D / 8, 1>;
@@ -147,16 +145,16 @@ __global__ void __launch_bounds__(NTHREADS)
             const float* KG = f.KG + ch * BT * D;
             const float* W = f.W + ch * BT * D;
             const float* AQK = f.AQK + ch * BT * BT;
-            for (int idx = tid; idx < BT * D; idx += NTHREADS) {
-                sM1[(idx / D) * LD + idx % D] = KG[idx];
-                sM2[(idx / D) * LD + idx % D] = W[idx];
-            }
-            for (int idx = tid; idx < BT * BT; idx += NTHREADS) sA[(idx / BT) * LA + idx % BT] = AQK[idx];
-            for (int idx = tid; idx < BT * VT; idx += NTHREADS) {
-                const int r = idx / VT, cc = idx % VT;
-                sO[r * LV + cc] = (r < len) ? ld(dout + ((size_t)(tok0 + r) * H + h) * D + v0 + cc) : 0.f;
-            }
-            if (tid < D) sLam[tid] = exp2f(f.GL[ch * D + tid]);
+            tile_copy<BT, D>([&](int r, int cc) { return ldg(KG + r * D + cc); },
+                             [&](int r, int cc, float x) { sM1[r * LD + cc] = x; });
+            tile_copy<BT, D>([&](int r, int cc) { return ldg(W + r * D + cc); },
+                             [&](int r, int cc, float x) { sM2[r * LD + cc] = x; });
+            tile_copy<BT, BT>([&](int r, int cc) { return ldg(AQK + r * BT + cc); },
+                              [&](int r, int cc, float x) { sA[r * LA + cc] = x; });
+            tile_copy<BT, VT>(
+                [&](int r, int cc) { return (r < len) ? ldg(dout + ((size_t)(tok0 + r) * H + h) * D + v0 + cc) : 0.f; },
+                [&](int r, int cc, float x) { sO[r * LV + cc] = x; });
+            if (tid < D) sLam[tid] = exp2f(ldg(f.GL + ch * D + tid));
         }
         __syncthreads();
         // R_bar = C_q^T dO + F S+bar ; record S+bar for the consumers
@@ -179,8 +177,10 @@ __global__ void __launch_bounds__(NTHREADS)
         {
             const float* AI = f.AINV + ch * BT * BT;
             const float* QG = f.QG + ch * BT * D;
-            for (int idx = tid; idx < BT * BT; idx += NTHREADS) sA[(idx / BT) * LA + idx % BT] = AI[idx];
-            for (int idx = tid; idx < BT * D; idx += NTHREADS) sM1[(idx / D) * LD + idx % D] = QG[idx];
+            tile_copy<BT, BT>([&](int r, int cc) { return ldg(AI + r * BT + cc); },
+                              [&](int r, int cc, float x) { sA[r * LA + cc] = x; });
+            tile_copy<BT, D>([&](int r, int cc) { return ldg(QG + r * D + cc); },
+                             [&](int r, int cc, float x) { sM1[r * LD + cc] = x; });
         }
         __syncthreads();
         // P = A^T R_bar
