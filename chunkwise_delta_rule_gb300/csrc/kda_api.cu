@@ -82,8 +82,8 @@ struct Layout {
     size_t piece = 0;   // time pieces of the tensor-core backward: two state adjoints, the claim counters
 };
 
-// The tensor-core path serves bf16 I/O at K = V = 128; everything else runs
-// the fp32 CUDA-core kernels.
+// The tensor-core path serves bf16 I/O at K = V = 128 (narrower bf16 widths reach it padded);
+// everything else runs the fp32 CUDA-core kernels.
 bool use_tc(const kda_problem* p) { return p->io == KDA_BF16 && p->K == 128; }
 
 Layout layout(const Dims& d) {
@@ -202,10 +202,14 @@ kda::Shape shape_of(const kda_problem* p, const Dims& d) {
     return s;
 }
 
-// Widths other than K = V = 64, 128 or 256 run zero-padded to D (0: no padding).
+// Widths other than K = V = 128 or 256 (and, fp32 I/O, 64) run zero-padded to D (0: no
+// padding): bf16 I/O at K <= 128 goes to 128, the tensor-core width; fp32 I/O to 64 when both
+// widths fit, else 128; K > 128 to 256.
 int pad_width(const kda_problem* p) {
-    if (p->K == p->V && (p->K == 64 || p->K == 128 || p->K == 256)) return 0;
+    const bool bf16 = p->io == KDA_BF16;
+    if (p->K == p->V && (p->K == 128 || p->K == 256 || (p->K == 64 && !bf16))) return 0;
     if (p->K > 128) return 256;
+    if (bf16) return 128;
     return (p->K <= 64 && p->V <= 64) ? 64 : 128;
 }
 // The padded buffers, in a fixed order after the inner problem's workspace (base NULL: size only).

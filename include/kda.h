@@ -39,9 +39,9 @@
  *    number of packed sequences.
  *  - Arguments are validated before anything is enqueued; on any error
  *    nothing is written and kda_last_error() describes the problem.
- *  - Widths: the chunked calls take any K <= 256 and V <= 4096 (K = V = 64,
- *    128 or 256 natively, other widths zero-padded to the next of those, V
- *    above 128 as value blocks, above 256 when K > 128; see kda_problem); the
+ *  - Widths: the chunked calls take any K <= 256 and V <= 4096 (K = V = 128
+ *    or 256 natively, and 64 with fp32 I/O; other widths zero-padded, V above
+ *    128 as value blocks, above 256 when K > 128; see kda_problem); the
  *    token-by-token call takes K = 64, 128, 160, 192 and 256.
  */
 #ifndef KDA_H_
@@ -77,17 +77,18 @@ typedef enum { KDA_GATE_NONE = 0, KDA_GATE_SCALAR = 1, KDA_GATE_CHANNEL = 2 } kd
 typedef struct {
     int B, T, H, K, V;          /* batch, tokens per sequence (total tokens when packed),
                                    heads, key width (1..256), value width (1..4096).
-                                   Other than K = V = 64, 128 or 256 the chunked calls
-                                   run zero-padded to 64 (K, V <= 64), 128 (K <= 128) or
-                                   256 (K > 128, the value side too). V above M runs as
+                                   Other than K = V = 128 or 256 (or 64 with fp32 I/O)
+                                   the chunked calls run zero-padded: bf16 I/O with
+                                   K <= 128 to 128, fp32 I/O to 64 (K, V <= 64) or 128,
+                                   K > 128 to 256 (the value side too). V above M runs as
                                    ceil(V / M) value blocks, M = 128 (K <= 128) or 256,
                                    each a value head of its own (the delta-rule update
                                    moves every value column of the state independently,
                                    "ReWY" paper, the state recurrence). bf16 I/O at
-                                   K = V = 128 runs on the tensor cores; every other
-                                   width and fp32 I/O on fp32 CUDA-core kernels. The
-                                   token-by-token call needs K = 64, 128, 160, 192 or 256
-                                   and V a multiple of 32. */
+                                   K <= 128 runs on the tensor cores; K > 128 and fp32
+                                   I/O on fp32 CUDA-core kernels. The token-by-token call
+                                   needs K = 64, 128, 160, 192 or 256 and V a multiple of
+                                   32. */
     int N;                      /* packed sequences (used only when cu_seqlens != NULL) */
     const int32_t *cu_seqlens;  /* device, N+1 non-decreasing token offsets, first 0,
                                    last B*T; NULL for equal-length sequences */

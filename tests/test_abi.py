@@ -210,8 +210,13 @@ def test_unequal_widths_pad_to_the_working_width():
     pad_b = pad_f + up(2 * T * H * D) + up(4 * 2 * H * D * D) + 3 * up(2 * T * H * D) + up(4 * T * H * D) \
         + up(4 * 2 * H * D * D)
     assert _ws(p, 1) == _ws(work, 1) + pad_b
-    small = _prob(K=32, V=48)           # both within 64: runs at 64
-    assert _ws(small, 0) > 0
+    # bf16 widths up to 128 all run at 128 (the tensor-core width), fp32 ones within 64 at 64
+    assert _ws(_prob(K=32, V=48), 0) == _ws(p, 0)
+    assert _ws(_prob(K=64, V=64), 0) == _ws(p, 0)
+    D = 64
+    pad64 = 3 * up(4 * T * H * D) + up(4 * T * H * D) + up(4 * T * H * D) + up(4 * 2 * H * D * D)
+    assert _ws(_prob(K=32, V=48, io=1), 0) == _ws(_prob(K=64, V=64, io=1), 0) + pad64
+    D = 128
     z = ctypes.c_void_p(0x3000)
     assert lib.kda_recurrent_fwd(ctypes.byref(p), z, None, None, None) == 2
     # key widths above 128 run at 256 (the value side too)
