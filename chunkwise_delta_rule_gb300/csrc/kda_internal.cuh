@@ -177,6 +177,74 @@ __device__ __forceinline__ void tile_gemm(float (&acc)[TM][TN], int k0, int k1, 
     }
 }
 
+// The same product with A row-major in shared memory, A(m, kk) = pa[m * lda + kk], rows of
+// 16-byte aligned storage (lda % 4 == 0): four steps of kk per 16-byte load of each of the
+// thread's rows (k0, k1 multiples of 4). Rows as TileMap, or with BLK as TileMapB (below);
+// columns as TileMap.
+template <int M, int N, int TM, int TN, bool BLK = false, class FB>
+__device__ __forceinline__ void tile_gemm_ar(float (&acc)[TM][TN], const float* pa, int lda, int k0, int k1, FB B) {
+    using TMp = TileMap<M, N, TM, TN>;
+    const int tm = TMp::tm(), tn = TMp::tn();
+#pragma unroll 1
+    for (int kk = k0; kk < k1; kk += 4) {
+        float4 a[TM];
+        float b[4][TN];
+#pragma unroll
+        for (int i = 0; i < TM; ++i) {
+            const int m = BLK ? tm * TM + i : tm + i * TMp::TMX;
+            a[i] = *reinterpret_cast<const float4*>(pa + m * lda + kk);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int j = 0; j < TN; ++j) b[q][j] = B(kk + q, tn + j * TMp::TNX);
+#pragma unroll
+        for (int i = 0; i < TM; ++i)
+#pragma unroll
+            for (int j = 0; j < TN; ++j) {
+                acc[i][j] = fmaf(a[i].x, b[0][j], acc[i][j]);
+                acc[i][j] = fmaf(a[i].y, b[1][j], acc[i][j]);
+                acc[i][j] = fmaf(a[i].z, b[2][j], acc[i][j]);
+                acc[i][j] = fmaf(a[i].w, b[3][j], acc[i][j]);
+            }
+    }
+}
+
+// Blocked row map: the thread's TM rows are consecutive, m_i = tm * TM + i (columns as TileMap).
+template <int M, int N, int TM, int TN>
+struct TileMapB {
+    using Base = TileMap<M, N, TM, TN>;
+    __device__ __forceinline__ static int row(int i) { return Base::tm() * TM + i; }
+    __device__ __forceinline__ static int col(int j) { return Base::col(j); }
+};
+
+// The product with A stored transposed in shared memory, A(m, kk) = pa[kk * lda + m] (lda % 4 == 0),
+// on the blocked row map: a thread's TM consecutive rows come in TM / 4 16-byte loads per kk.
+template <int M, int N, int TM, int TN, class FB>
+__device__ __forceinline__ void tile_gemm_at(float (&acc)[TM][TN], const float* pa, int lda, int k0, int k1, FB B) {
+    static_assert(TM % 4 == 0, "blocked rows come four at a time");
+    using TMp = TileMap<M, N, TM, TN>;
+    const int m0 = TMp::tm() * TM, tn = TMp::tn();
+#pragma unroll 2
+    for (int kk = k0; kk < k1; ++kk) {
+        float4 a[TM / 4];
+        float b[TN];
+#pragma unroll
+        for (int i = 0; i < TM / 4; ++i) a[i] = *reinterpret_cast<const float4*>(pa + kk * lda + m0 + 4 * i);
+#pragma unroll
+        for (int j = 0; j < TN; ++j) b[j] = B(kk, tn + j * TMp::TNX);
+#pragma unroll
+        for (int i = 0; i < TM / 4; ++i)
+#pragma unroll
+            for (int j = 0; j < TN; ++j) {
+                acc[4 * i][j] = fmaf(a[i].x, b[j], acc[4 * i][j]);
+                acc[4 * i + 1][j] = fmaf(a[i].y, b[j], acc[4 * i + 1][j]);
+                acc[4 * i + 2][j] = fmaf(a[i].z, b[j], acc[4 * i + 2][j]);
+                acc[4 * i + 3][j] = fmaf(a[i].w, b[j], acc[4 * i + 3][j]);
+            }
+    }
+}
+
 template <int TM, int TN>
 __device__ __forceinline__ void zero(float (&acc)[TM][TN]) {
 #pragma unroll

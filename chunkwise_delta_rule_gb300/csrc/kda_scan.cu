@@ -17,11 +17,14 @@ namespace {
 
 constexpr int VT = 32;  // value columns per CTA
 
+// Row strides: the A operands of the products (W, Q_g, F, C_q, A) sit in rows of 16-byte aligned
+// storage (D + 4, BT + 4) so that they are read four elements per load; the B operands (S, U/R,
+// dO, R_bar) in rows of VT + 1.
 template <typename TI, int D, int MODE>
 __global__ void __launch_bounds__(NTHREADS)
     k_fwd_scan(Shape s, const float* __restrict__ h0, Table t, Fwd f, TI* __restrict__ o,
                float* __restrict__ ht) {
-    constexpr int LD = D + 1, LV = VT + 1, LA = BT + 1;
+    constexpr int LD = D + 4, LV = VT + 1, LA = BT + 4;
     extern __shared__ float smem[];
     float* sS = smem;             // [D][LV] state tile
     float* sM = sS + D * LV;      // [BT][LD] W, then Q_g, then F
@@ -36,7 +39,7 @@ __global__ void __launch_bounds__(NTHREADS)
                      [&](int r, int cc, float x) { sS[r * LV + cc] = x; });
     const int c0 = t.seq_chunk0[nseq], c1 = t.seq_chunk0[nseq + 1];
     using TR = TileMap<BT, VT, 8, 1>;
-    using TS = TileMap<D, VT, D / 8, 1>;
+    using TS = TileMapB<D, VT, D / 8, 1>;
     for (int c = c0; c < c1; ++c) {
         const size_t ch = (size_t)c * H + h;
         const int len = t.chunk_len[c], tok0 = t.chunk_tok0[c];
@@ -52,8 +55,7 @@ __global__ void __launch_bounds__(NTHREADS)
         {
             float acc[8][1];
             zero(acc);
-            tile_gemm<BT, VT, 8, 1>(acc, 0, D, [&](int m, int kk) { return sM[m * LD + kk]; },
-                                    [&](int kk, int nn) { return sS[kk * LV + nn]; });
+            tile_gemm_ar<BT, VT, 8, 1>(acc, sM, LD, 0, D, [&](int kk, int nn) { return sS[kk * LV + nn]; });
 #pragma unroll
             for (int ii = 0; ii < 8; ++ii) {
                 const int m = TR::row(ii), nn = TR::col(0);
@@ -80,10 +82,8 @@ __global__ void __launch_bounds__(NTHREADS)
             __syncthreads();
             float acc[8][1];
             zero(acc);
-            tile_gemm<BT, VT, 8, 1>(acc, 0, D, [&](int m, int kk) { return sM[m * LD + kk]; },
-                                    [&](int kk, int nn) { return sS[kk * LV + nn]; });
-            tile_gemm<BT, VT, 8, 1>(acc, 0, BT, [&](int m, int kk) { return sA[m * LA + kk]; },
-                                    [&](int kk, int nn) { return sR[kk * LV + nn]; });
+            tile_gemm_ar<BT, VT, 8, 1>(acc, sM, LD, 0, D, [&](int kk, int nn) { return sS[kk * LV + nn]; });
+            tile_gemm_ar<BT, VT, 8, 1>(acc, sA, LA, 0, BT, [&](int kk, int nn) { return sR[kk * LV + nn]; });
 #pragma unroll
             for (int ii = 0; ii < 8; ++ii) {
                 const int m = TR::row(ii), nn = TR::col(0);
@@ -98,8 +98,7 @@ __global__ void __launch_bounds__(NTHREADS)
             __syncthreads();
             float acc[D / 8][1];
             zero(acc);
-            tile_gemm<D, VT, D / 8, 1>(acc, 0, BT, [&](int m, int kk) { return sM[kk * LD + m]; },
-                                       [&](int kk, int nn) { return sR[kk * LV + nn]; });
+            tile_gemm_at<D, VT, D / 8, 1>(acc, sM, LD, 0, BT, [&](int kk, int nn) { return sR[kk * LV + nn]; });
 #pragma unroll
             for (int ii = 0; ii < D / 8; ++ii) {
                 const int m = TS::row(ii), nn = TS::col(0);
@@ -120,7 +119,7 @@ template <typename TI, int D>
 __global__ void __launch_bounds__(NTHREADS)
     k_bwd_scan(Shape s, const TI* __restrict__ dout, const float* __restrict__ dht, Table t, Fwd f,
                Bwd b, float* __restrict__ dh0) {
-    constexpr int LD = D + 1, LV = VT + 1, LA = BT + 1;
+    constexpr int LD = D + 4, LV = VT + 1, LA = BT + 4;
     extern __shared__ float smem[];
     float* sSb = smem;             // [D][LV] state adjoint tile
     float* sM1 = sSb + D * LV;     // [BT][LD] F, then Q_g
@@ -136,8 +135,8 @@ __global__ void __launch_bounds__(NTHREADS)
     tile_copy<D, VT>([&](int r, int cc) { return dht ? ldg(dht + st_off + (size_t)r * D + v0 + cc) : 0.f; },
                      [&](int r, int cc, float x) { sSb[r * LV + cc] = x; });
     const int c0 = t.seq_chunk0[nseq], c1 = t.seq_chunk0[nseq + 1];
-    using TR = TileMap<BT, VT, 8, 1>;
-    using TS = TileMap<D, VT, D / 8, 1>;
+    using TR = TileMapB<BT, VT, 8, 1>;
+    using TS = TileMapB<D, VT, D / 8, 1>;
     for (int c = c1 - 1; c >= c0; --c) {
         const size_t ch = (size_t)c * H + h;
         const int len = t.chunk_len[c], tok0 = t.chunk_tok0[c];
@@ -161,10 +160,8 @@ __global__ void __launch_bounds__(NTHREADS)
         {
             float acc[8][1];
             zero(acc);
-            tile_gemm<BT, VT, 8, 1>(acc, 0, BT, [&](int m, int kk) { return sA[kk * LA + m]; },
-                                    [&](int kk, int nn) { return sO[kk * LV + nn]; });
-            tile_gemm<BT, VT, 8, 1>(acc, 0, D, [&](int m, int kk) { return sM1[m * LD + kk]; },
-                                    [&](int kk, int nn) { return sSb[kk * LV + nn]; });
+            tile_gemm_at<BT, VT, 8, 1>(acc, sA, LA, 0, BT, [&](int kk, int nn) { return sO[kk * LV + nn]; });
+            tile_gemm_ar<BT, VT, 8, 1, true>(acc, sM1, LD, 0, D, [&](int kk, int nn) { return sSb[kk * LV + nn]; });
 #pragma unroll
             for (int ii = 0; ii < 8; ++ii) sRb[TR::row(ii) * LV + TR::col(0)] = acc[ii][0];
             float* SBP = b.SBP + ch * D * D;
@@ -187,8 +184,7 @@ __global__ void __launch_bounds__(NTHREADS)
         {
             float acc[8][1];
             zero(acc);
-            tile_gemm<BT, VT, 8, 1>(acc, 0, BT, [&](int m, int kk) { return sA[kk * LA + m]; },
-                                    [&](int kk, int nn) { return sRb[kk * LV + nn]; });
+            tile_gemm_at<BT, VT, 8, 1>(acc, sA, LA, 0, BT, [&](int kk, int nn) { return sRb[kk * LV + nn]; });
             float* P = b.P + ch * BT * D;
 #pragma unroll
             for (int ii = 0; ii < 8; ++ii) P[(size_t)TR::row(ii) * D + v0 + TR::col(0)] = acc[ii][0];
@@ -198,10 +194,8 @@ __global__ void __launch_bounds__(NTHREADS)
             float acc[D / 8][1], acc2[D / 8][1];
             zero(acc);
             zero(acc2);
-            tile_gemm<D, VT, D / 8, 1>(acc, 0, BT, [&](int m, int kk) { return sM1[kk * LD + m]; },
-                                       [&](int kk, int nn) { return sO[kk * LV + nn]; });
-            tile_gemm<D, VT, D / 8, 1>(acc2, 0, BT, [&](int m, int kk) { return sM2[kk * LD + m]; },
-                                       [&](int kk, int nn) { return sRb[kk * LV + nn]; });
+            tile_gemm_at<D, VT, D / 8, 1>(acc, sM1, LD, 0, BT, [&](int kk, int nn) { return sO[kk * LV + nn]; });
+            tile_gemm_at<D, VT, D / 8, 1>(acc2, sM2, LD, 0, BT, [&](int kk, int nn) { return sRb[kk * LV + nn]; });
 #pragma unroll
             for (int ii = 0; ii < D / 8; ++ii) {
                 const int m = TS::row(ii), nn = TS::col(0);
@@ -220,7 +214,7 @@ __global__ void __launch_bounds__(NTHREADS)
 
 template <typename TI, int D, int MODE>
 cudaError_t run_fwd(const Shape& s, const float* h0, Table t, Fwd f, void* o, float* ht, cudaStream_t st) {
-    constexpr int LD = D + 1, LV = VT + 1, LA = BT + 1;
+    constexpr int LD = D + 4, LV = VT + 1, LA = BT + 4;
     constexpr size_t smem = sizeof(float) * (D * LV + BT * LD + BT * LV + BT * LA + D);
     auto kern = k_fwd_scan<TI, D, MODE>;
     cudaError_t e = set_smem_once<k_fwd_scan<TI, D, MODE>>(smem);
@@ -243,7 +237,7 @@ cudaError_t run_fwd_mode(int mode, const Shape& s, const float* h0, Table t, Fwd
 template <typename TI, int D>
 cudaError_t run_bwd(const Shape& s, const void* dout, const float* dht, Table t, Fwd f, Bwd b,
                     float* dh0, cudaStream_t st) {
-    constexpr int LD = D + 1, LV = VT + 1, LA = BT + 1;
+    constexpr int LD = D + 4, LV = VT + 1, LA = BT + 4;
     constexpr size_t smem = sizeof(float) * (D * LV + 2 * BT * LD + 2 * BT * LV + BT * LA + D);
     auto kern = k_bwd_scan<TI, D>;
     cudaError_t e = set_smem_once<k_bwd_scan<TI, D>>(smem);
