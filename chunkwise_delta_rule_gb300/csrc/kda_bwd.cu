@@ -41,7 +41,9 @@ __device__ __forceinline__ void dstate_chunk(int c, int h, const Shape& s, const
                                              TI* __restrict__ dv, const Gdn2& gd) {
     constexpr int DC = D > 128 ? 128 : D;   // columns per block
     constexpr int NB = D / DC;              // blocks
-    constexpr int LD = DC + 1, LS = SL + 1;
+    // rows of 16-byte aligned storage (both operands of every product are read four elements of
+    // the contraction per load), strides 4 mod 32 words
+    constexpr int LD = DC + 4, LS = SL + 4;
     extern __shared__ float smem[];
     float* sO = smem;              // [BT][LD] dO, one value block
     float* sP = sO + BT * LD;      // [BT][LD] P
@@ -108,10 +110,8 @@ __device__ __forceinline__ void dstate_chunk(int c, int h, const Shape& s, const
                     }
                 }
             }
-            tile_gemm<BT, BT, 8, 2>(acc, 0, DC, [&](int m, int kk) { return sP[m * LD + kk]; },
-                                    [&](int kk, int nn) { return sR[nn * LD + kk]; });
-            tile_gemm<BT, BT, 8, 2>(acc2, 0, DC, [&](int m, int kk) { return sO[m * LD + kk]; },
-                                    [&](int kk, int nn) { return sR[nn * LD + kk]; });
+            tile_gemm_nt<BT, BT, 8, 2>(acc, sP, LD, sR, LD, 0, DC);
+            tile_gemm_nt<BT, BT, 8, 2>(acc2, sO, LD, sR, LD, 0, DC);
         }
 #pragma unroll
         for (int i = 0; i < RW; ++i) {
@@ -165,12 +165,9 @@ __device__ __forceinline__ void dstate_chunk(int c, int h, const Shape& s, const
                 tile_copy<DC, SL>([&](int r, int cc) { return ldg(SBP + e(r, cc)); },
                                   [&](int r, int cc, float x) { sT[r * LS + cc] = x; });
                 __syncthreads();
-                tile_gemm<BT, DC, 8, TN>(aQ, 0, SL, [&](int m, int kk) { return sO[m * LD + vs + kk]; },
-                                         [&](int kk, int nn) { return sS[nn * LS + kk]; });
-                tile_gemm<BT, DC, 8, TN>(aP, 0, SL, [&](int m, int kk) { return sP[m * LD + vs + kk]; },
-                                         [&](int kk, int nn) { return sS[nn * LS + kk]; });
-                tile_gemm<BT, DC, 8, TN>(aF, 0, SL, [&](int m, int kk) { return sR[m * LD + vs + kk]; },
-                                         [&](int kk, int nn) { return sT[nn * LS + kk]; });
+                tile_gemm_nt<BT, DC, 8, TN>(aQ, sO + vs, LD, sS, LS, 0, SL);
+                tile_gemm_nt<BT, DC, 8, TN>(aP, sP + vs, LD, sS, LS, 0, SL);
+                tile_gemm_nt<BT, DC, 8, TN>(aF, sR + vs, LD, sT, LS, 0, SL);
                 for (int cc = kpart; cc < SL; cc += TPR) lam = fmaf(sS[kr * LS + cc], sT[kr * LS + cc], lam);
             }
         }
@@ -201,7 +198,7 @@ __device__ __forceinline__ void intra_chunk(int c, int h, const Shape& s, const 
                                             float* __restrict__ dg, const Gdn2& gd) {
     constexpr int DC = D > 128 ? 128 : D;   // feature columns per pass
     constexpr int NB = D / DC;              // passes
-    constexpr int LD = DC + 1, LA = BT + 1;
+    constexpr int LD = DC + 1, LA = BT + 4;   // D and H_q rows 16-byte aligned (read four at a time)
     extern __shared__ float smem[];
     float* sK = smem;               // [BT][LD] keys of the column block
     float* sQ = sK + BT * LD;       // [BT][LD] queries
@@ -312,10 +309,8 @@ __device__ __forceinline__ void intra_chunk(int c, int h, const Shape& s, const 
                 sF3[r * LD + col] = sK[r * LD + col] * zeta(r, col);
             }
             __syncthreads();
-            tile_gemm<BT, DC, 8, TN>(aQ, 0, BT, [&](int m, int kk) { return sHQ[m * LA + kk]; },
-                                     [&](int kk, int nn) { return sF3[kk * LD + nn]; });
-            tile_gemm<BT, DC, 8, TN>(aE, 0, BT, [&](int m, int kk) { return sDM[m * LA + kk]; },
-                                     [&](int kk, int nn) { return sF3[kk * LD + nn]; });
+            tile_gemm_ar<BT, DC, 8, TN>(aQ, sHQ, LA, 0, BT, [&](int kk, int nn) { return sF3[kk * LD + nn]; });
+            tile_gemm_ar<BT, DC, 8, TN>(aE, sDM, LA, 0, BT, [&](int kk, int nn) { return sF3[kk * LD + nn]; });
 #pragma unroll
             for (int ii = 0; ii < 8; ++ii)
 #pragma unroll
@@ -570,7 +565,7 @@ template <typename TI, typename IT, int D>
 cudaError_t run_dstate(const Shape& s, const void* dout, const void* v, const void* beta, Table t,
                        const IT* P, const IT* R, const IT* S, const IT* SB, const int32_t* list, Bwd b,
                        void* dv, cudaStream_t st, const Gdn2& gd = Gdn2{}) {
-    constexpr int DC = D > 128 ? 128 : D, LD = DC + 1, LS = SL + 1;
+    constexpr int DC = D > 128 ? 128 : D, LD = DC + 4, LS = SL + 4;
     constexpr size_t smem = sizeof(float) * (3 * BT * LD + 2 * DC * LS);
     auto kern = k_bwd_dstate<TI, IT, D>;
     cudaError_t e = set_smem_once<k_bwd_dstate<TI, IT, D>>(smem);
@@ -585,7 +580,7 @@ template <typename TI, int D, int GATE>
 cudaError_t run_intra(const Shape& s, const void* q, const void* k, const void* beta, const float* g,
                       Table t, const int32_t* list, Bwd b, void* dq, void* dk, void* dbeta, float* dg,
                       cudaStream_t st, const Gdn2& gd) {
-    constexpr int DC = D > 128 ? 128 : D, LD = DC + 1, LA = BT + 1;
+    constexpr int DC = D > 128 ? 128 : D, LD = DC + 1, LA = BT + 4;
     constexpr size_t smem = sizeof(float) * (5 * BT * LD + 2 * BT * LA + 2 * BT + DC);
     auto kern = k_bwd_intra<TI, D, GATE>;
     cudaError_t e = set_smem_once<k_bwd_intra<TI, D, GATE>>(smem);

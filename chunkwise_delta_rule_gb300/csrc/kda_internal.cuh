@@ -210,6 +210,34 @@ __device__ __forceinline__ void tile_gemm_ar(float (&acc)[TM][TN], const float* 
     }
 }
 
+// The product with both operands contiguous along the contraction: A(m, kk) = pa[m * lda + kk],
+// B(kk, n) = pb[n * ldb + kk], four steps of kk per 16-byte load of each row (lda, ldb % 4 == 0;
+// ldb % 32 == 4 puts the loads of eight consecutive columns on distinct banks). Rows and columns
+// as TileMap; k0, k1 multiples of 4.
+template <int M, int N, int TM, int TN>
+__device__ __forceinline__ void tile_gemm_nt(float (&acc)[TM][TN], const float* pa, int lda, const float* pb, int ldb,
+                                             int k0, int k1) {
+    using TMp = TileMap<M, N, TM, TN>;
+    const int tm = TMp::tm(), tn = TMp::tn();
+#pragma unroll 1
+    for (int kk = k0; kk < k1; kk += 4) {
+        float4 a[TM], b[TN];
+#pragma unroll
+        for (int i = 0; i < TM; ++i) a[i] = *reinterpret_cast<const float4*>(pa + (tm + i * TMp::TMX) * lda + kk);
+#pragma unroll
+        for (int j = 0; j < TN; ++j) b[j] = *reinterpret_cast<const float4*>(pb + (tn + j * TMp::TNX) * ldb + kk);
+#pragma unroll
+        for (int i = 0; i < TM; ++i)
+#pragma unroll
+            for (int j = 0; j < TN; ++j) {
+                acc[i][j] = fmaf(a[i].x, b[j].x, acc[i][j]);
+                acc[i][j] = fmaf(a[i].y, b[j].y, acc[i][j]);
+                acc[i][j] = fmaf(a[i].z, b[j].z, acc[i][j]);
+                acc[i][j] = fmaf(a[i].w, b[j].w, acc[i][j]);
+            }
+    }
+}
+
 // Blocked row map: the thread's TM rows are consecutive, m_i = tm * TM + i (columns as TileMap).
 template <int M, int N, int TM, int TN>
 struct TileMapB {

@@ -29,8 +29,10 @@ __device__ __forceinline__ void prep_chunk(int c, int h, const Shape& s, const T
                                            const Table& t, const Fwd& f, const FwdTC& ft, const Gdn2& gd) {
     constexpr int DC = D > 128 ? 128 : D;   // feature columns per pass
     constexpr int NB = D / DC;              // passes
-    constexpr int LD = DC + 1;              // padded row stride of [BT x DC] tiles
-    constexpr int LA = BT + 1;              // padded row stride of [BT x BT] tiles
+    // row strides of [BT x DC] and [BT x BT] tiles: 16-byte aligned rows, 4 mod 32 words, so that
+    // the products read both operands four elements of the contraction per load
+    constexpr int LD = DC + 4;
+    constexpr int LA = BT + 4;
     extern __shared__ float smem[];
     float* sK = smem;               // [BT][LD] keys (fp32) of the column block
     float* sG = sK + BT * LD;       // [BT][LD] cumulative log2-decay
@@ -111,9 +113,9 @@ __device__ __forceinline__ void prep_chunk(int c, int h, const Shape& s, const T
             __syncthreads();
             float acc[4][2];
             zero(acc);
-            tile_gemm<2 * BC, BT, 4, 2>(
-                acc, 0, DC, [&](int m, int kk) { return sL[m * LD + kk]; },
-                [&](int kk, int nn) { return nn < ncol ? sR[nn * LD + kk] : 0.f; });
+            // columns j >= ncol read rows of sR this sub-chunk did not write: they lie above the
+            // diagonal (j > i) and are masked out below
+            tile_gemm_nt<2 * BC, BT, 4, 2>(acc, sL, LD, sR, LD, 0, DC);
             using TMp = TileMap<2 * BC, BT, 4, 2>;
             // a thread owns the same (i, j) entries in every pass, so the block sums need no barrier
 #pragma unroll
@@ -209,8 +211,7 @@ __device__ __forceinline__ void prep_chunk(int c, int h, const Shape& s, const T
         {
             float acc[8][TN];
             zero(acc);
-            tile_gemm<BT, DC, 8, TN>(acc, 0, BT, [&](int m, int kk) { return sAi[m * LA + kk]; },
-                                     [&](int kk, int nn) { return sR[kk * LD + nn]; });
+            tile_gemm_ar<BT, DC, 8, TN>(acc, sAi, LA, 0, BT, [&](int kk, int nn) { return sR[kk * LD + nn]; });
 #pragma unroll
             for (int ii = 0; ii < 8; ++ii)
 #pragma unroll
@@ -226,8 +227,7 @@ __device__ __forceinline__ void prep_chunk(int c, int h, const Shape& s, const T
         {
             float acc[8][TN];
             zero(acc);
-            tile_gemm<BT, DC, 8, TN>(acc, 0, BT, [&](int m, int kk) { return sAi[m * LA + kk]; },
-                                     [&](int kk, int nn) { return sQ[kk * LD + nn]; });
+            tile_gemm_ar<BT, DC, 8, TN>(acc, sAi, LA, 0, BT, [&](int kk, int nn) { return sQ[kk * LD + nn]; });
             float* U = (TCOUT ? ft.U : f.U) + ch * BT * D;
 #pragma unroll
             for (int ii = 0; ii < 8; ++ii)
@@ -258,7 +258,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 template <typename TI, int D, int GATE, bool TCOUT>
 cudaError_t run(const Shape& s, const void* q, const void* k, const void* v, const void* beta,
                 const float* g, Table t, Fwd f, FwdTC ft, cudaStream_t st, const Gdn2& gd = Gdn2{}) {
-    constexpr int DC = D > 128 ? 128 : D, LD = DC + 1, LA = BT + 1;
+    constexpr int DC = D > 128 ? 128 : D, LD = DC + 4, LA = BT + 4;
     constexpr size_t smem = sizeof(float) * (4 * BT * LD + 2 * BC * LD + (D > DC ? 3 : 2) * BT * LA + BT);
     auto kern = k_prep<TI, D, GATE, TCOUT>;
     cudaError_t e = set_smem_once<k_prep<TI, D, GATE, TCOUT>>(smem);
