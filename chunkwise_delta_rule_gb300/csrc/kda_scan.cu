@@ -17,17 +17,28 @@ namespace {
 
 constexpr int VT = 32;  // value columns per CTA
 
-// Row strides: the A operands of the products (W, Q_g, F, C_q, A) sit in rows of 16-byte aligned
-// storage (D + 4, BT + 4) so that they are read four elements per load; the B operands (S, U/R,
-// dO, R_bar) in rows of VT + 1.
+// Key blocks: the [BT x D] operands (W, Q_g, F) are staged DK = min(D, 128) keys at a time in one
+// [BT][DK] buffer, so that two CTAs share an SM at every width; the products over the key width
+// add up block by block, the state update runs block by block over its rows. Row strides: the
+// A operands of the products (W, Q_g, F, C_q, A) sit in rows of 16-byte aligned storage (DK + 4,
+// BT + 4) so that they are read four elements per load; the B operands (S, U/R, dO, R_bar) in
+// rows of VT + 1.
+template <int D>
+struct ScanDims {
+    static constexpr int DK = D > 128 ? 128 : D;   // keys per staged block
+    static constexpr int NKB = D / DK;             // key blocks
+    static constexpr int LD = DK + 4, LV = VT + 1, LA = BT + 4;
+};
+
 template <typename TI, int D, int MODE>
-__global__ void __launch_bounds__(NTHREADS)
+__global__ void __launch_bounds__(NTHREADS, 2)
     k_fwd_scan(Shape s, const float* __restrict__ h0, Table t, Fwd f, TI* __restrict__ o,
                float* __restrict__ ht) {
-    constexpr int LD = D + 4, LV = VT + 1, LA = BT + 4;
+    using SD = ScanDims<D>;
+    constexpr int DK = SD::DK, NKB = SD::NKB, LD = SD::LD, LV = SD::LV, LA = SD::LA;
     extern __shared__ float smem[];
     float* sS = smem;             // [D][LV] state tile
-    float* sM = sS + D * LV;      // [BT][LD] W, then Q_g, then F
+    float* sM = sS + D * LV;      // [BT][LD] one key block of W, then Q_g, then F
     float* sR = sM + BT * LD;     // [BT][LV] U, then R
     float* sA = sR + BT * LV;     // [BT][LA] C_q
     float* sLam = sA + BT * LA;   // [D]
@@ -39,23 +50,32 @@ __global__ void __launch_bounds__(NTHREADS)
                      [&](int r, int cc, float x) { sS[r * LV + cc] = x; });
     const int c0 = t.seq_chunk0[nseq], c1 = t.seq_chunk0[nseq + 1];
     using TR = TileMap<BT, VT, 8, 1>;
-    using TS = TileMapB<D, VT, D / 8, 1>;
+    using TS = TileMapB<DK, VT, DK / 8, 1>;
+    // one key block of a [BT][D] operand into sM
+    auto stage = [&](const float* X, int kb) {
+        tile_copy<BT, DK>([&](int r, int cc) { return ldg(X + r * D + kb * DK + cc); },
+                          [&](int r, int cc, float x) { sM[r * LD + cc] = x; });
+    };
     for (int c = c0; c < c1; ++c) {
         const size_t ch = (size_t)c * H + h;
         const int len = t.chunk_len[c], tok0 = t.chunk_tok0[c];
         const float* W = f.W + ch * BT * D;
         const float* U = f.U + ch * BT * D;
-        tile_copy<BT, D>([&](int r, int cc) { return ldg(W + r * D + cc); },
-                         [&](int r, int cc, float x) { sM[r * LD + cc] = x; });
         tile_copy<BT, VT>([&](int r, int cc) { return ldg(U + (size_t)r * D + v0 + cc); },
                           [&](int r, int cc, float x) { sR[r * LV + cc] = x; });
         if (tid < D) sLam[tid] = exp2f(ldg(f.GL + ch * D + tid));
-        __syncthreads();
         // R = U - W S
         {
             float acc[8][1];
             zero(acc);
-            tile_gemm_ar<BT, VT, 8, 1>(acc, sM, LD, 0, D, [&](int kk, int nn) { return sS[kk * LV + nn]; });
+#pragma unroll 1
+            for (int kb = 0; kb < NKB; ++kb) {
+                if (kb > 0) __syncthreads();   // the previous block is read
+                stage(W, kb);
+                __syncthreads();
+                tile_gemm_ar<BT, VT, 8, 1>(acc, sM, LD, 0, DK,
+                                           [&](int kk, int nn) { return sS[(kb * DK + kk) * LV + nn]; });
+            }
 #pragma unroll
             for (int ii = 0; ii < 8; ++ii) {
                 const int m = TR::row(ii), nn = TR::col(0);
@@ -75,14 +95,18 @@ __global__ void __launch_bounds__(NTHREADS)
         if (MODE & 1) {
             const float* QG = f.QG + ch * BT * D;
             const float* AQK = f.AQK + ch * BT * BT;
-            tile_copy<BT, D>([&](int r, int cc) { return ldg(QG + r * D + cc); },
-                             [&](int r, int cc, float x) { sM[r * LD + cc] = x; });
             tile_copy<BT, BT>([&](int r, int cc) { return ldg(AQK + r * BT + cc); },
                               [&](int r, int cc, float x) { sA[r * LA + cc] = x; });
-            __syncthreads();
             float acc[8][1];
             zero(acc);
-            tile_gemm_ar<BT, VT, 8, 1>(acc, sM, LD, 0, D, [&](int kk, int nn) { return sS[kk * LV + nn]; });
+#pragma unroll 1
+            for (int kb = 0; kb < NKB; ++kb) {
+                if (kb > 0) __syncthreads();
+                stage(QG, kb);
+                __syncthreads();
+                tile_gemm_ar<BT, VT, 8, 1>(acc, sM, LD, 0, DK,
+                                           [&](int kk, int nn) { return sS[(kb * DK + kk) * LV + nn]; });
+            }
             tile_gemm_ar<BT, VT, 8, 1>(acc, sA, LA, 0, BT, [&](int kk, int nn) { return sR[kk * LV + nn]; });
 #pragma unroll
             for (int ii = 0; ii < 8; ++ii) {
@@ -91,18 +115,22 @@ __global__ void __launch_bounds__(NTHREADS)
             }
             __syncthreads();
         }
+        // S <- diag(lambda) S + F^T R, one key block of rows at a time
         {
             const float* KG = f.KG + ch * BT * D;
-            tile_copy<BT, D>([&](int r, int cc) { return ldg(KG + r * D + cc); },
-                             [&](int r, int cc, float x) { sM[r * LD + cc] = x; });
-            __syncthreads();
-            float acc[D / 8][1];
-            zero(acc);
-            tile_gemm_at<D, VT, D / 8, 1>(acc, sM, LD, 0, BT, [&](int kk, int nn) { return sR[kk * LV + nn]; });
+#pragma unroll 1
+            for (int kb = 0; kb < NKB; ++kb) {
+                if (kb > 0) __syncthreads();
+                stage(KG, kb);
+                __syncthreads();
+                float acc[DK / 8][1];
+                zero(acc);
+                tile_gemm_at<DK, VT, DK / 8, 1>(acc, sM, LD, 0, BT, [&](int kk, int nn) { return sR[kk * LV + nn]; });
 #pragma unroll
-            for (int ii = 0; ii < D / 8; ++ii) {
-                const int m = TS::row(ii), nn = TS::col(0);
-                sS[m * LV + nn] = sLam[m] * sS[m * LV + nn] + acc[ii][0];
+                for (int ii = 0; ii < DK / 8; ++ii) {
+                    const int m = kb * DK + TS::row(ii), nn = TS::col(0);
+                    sS[m * LV + nn] = sLam[m] * sS[m * LV + nn] + acc[ii][0];
+                }
             }
         }
         __syncthreads();
@@ -116,15 +144,15 @@ __global__ void __launch_bounds__(NTHREADS)
 }
 
 template <typename TI, int D>
-__global__ void __launch_bounds__(NTHREADS)
+__global__ void __launch_bounds__(NTHREADS, 2)
     k_bwd_scan(Shape s, const TI* __restrict__ dout, const float* __restrict__ dht, Table t, Fwd f,
                Bwd b, float* __restrict__ dh0) {
-    constexpr int LD = D + 4, LV = VT + 1, LA = BT + 4;
+    using SD = ScanDims<D>;
+    constexpr int DK = SD::DK, NKB = SD::NKB, LD = SD::LD, LV = SD::LV, LA = SD::LA;
     extern __shared__ float smem[];
     float* sSb = smem;             // [D][LV] state adjoint tile
-    float* sM1 = sSb + D * LV;     // [BT][LD] F, then Q_g
-    float* sM2 = sM1 + BT * LD;    // [BT][LD] W
-    float* sO = sM2 + BT * LD;     // [BT][LV] dO tile
+    float* sM = sSb + D * LV;      // [BT][LD] one key block of F, then Q_g, then W
+    float* sO = sM + BT * LD;      // [BT][LV] dO tile
     float* sRb = sO + BT * LV;     // [BT][LV] R_bar
     float* sA = sRb + BT * LV;     // [BT][LA] C_q, then A
     float* sLam = sA + BT * LA;    // [D]
@@ -136,18 +164,19 @@ __global__ void __launch_bounds__(NTHREADS)
                      [&](int r, int cc, float x) { sSb[r * LV + cc] = x; });
     const int c0 = t.seq_chunk0[nseq], c1 = t.seq_chunk0[nseq + 1];
     using TR = TileMapB<BT, VT, 8, 1>;
-    using TS = TileMapB<D, VT, D / 8, 1>;
+    using TS = TileMapB<DK, VT, DK / 8, 1>;
+    auto stage = [&](const float* X, int kb) {
+        tile_copy<BT, DK>([&](int r, int cc) { return ldg(X + r * D + kb * DK + cc); },
+                          [&](int r, int cc, float x) { sM[r * LD + cc] = x; });
+    };
     for (int c = c1 - 1; c >= c0; --c) {
         const size_t ch = (size_t)c * H + h;
         const int len = t.chunk_len[c], tok0 = t.chunk_tok0[c];
+        const float* KG = f.KG + ch * BT * D;
+        const float* QG = f.QG + ch * BT * D;
+        const float* W = f.W + ch * BT * D;
         {
-            const float* KG = f.KG + ch * BT * D;
-            const float* W = f.W + ch * BT * D;
             const float* AQK = f.AQK + ch * BT * BT;
-            tile_copy<BT, D>([&](int r, int cc) { return ldg(KG + r * D + cc); },
-                             [&](int r, int cc, float x) { sM1[r * LD + cc] = x; });
-            tile_copy<BT, D>([&](int r, int cc) { return ldg(W + r * D + cc); },
-                             [&](int r, int cc, float x) { sM2[r * LD + cc] = x; });
             tile_copy<BT, BT>([&](int r, int cc) { return ldg(AQK + r * BT + cc); },
                               [&](int r, int cc, float x) { sA[r * LA + cc] = x; });
             tile_copy<BT, VT>(
@@ -155,13 +184,20 @@ __global__ void __launch_bounds__(NTHREADS)
                 [&](int r, int cc, float x) { sO[r * LV + cc] = x; });
             if (tid < D) sLam[tid] = exp2f(ldg(f.GL + ch * D + tid));
         }
-        __syncthreads();
         // R_bar = C_q^T dO + F S+bar ; record S+bar for the consumers
         {
             float acc[8][1];
             zero(acc);
-            tile_gemm_at<BT, VT, 8, 1>(acc, sA, LA, 0, BT, [&](int kk, int nn) { return sO[kk * LV + nn]; });
-            tile_gemm_ar<BT, VT, 8, 1, true>(acc, sM1, LD, 0, D, [&](int kk, int nn) { return sSb[kk * LV + nn]; });
+#pragma unroll 1
+            for (int kb = 0; kb < NKB; ++kb) {
+                if (kb > 0) __syncthreads();
+                stage(KG, kb);
+                __syncthreads();
+                if (kb == 0)
+                    tile_gemm_at<BT, VT, 8, 1>(acc, sA, LA, 0, BT, [&](int kk, int nn) { return sO[kk * LV + nn]; });
+                tile_gemm_ar<BT, VT, 8, 1, true>(acc, sM, LD, 0, DK,
+                                                 [&](int kk, int nn) { return sSb[(kb * DK + kk) * LV + nn]; });
+            }
 #pragma unroll
             for (int ii = 0; ii < 8; ++ii) sRb[TR::row(ii) * LV + TR::col(0)] = acc[ii][0];
             float* SBP = b.SBP + ch * D * D;
@@ -173,11 +209,8 @@ __global__ void __launch_bounds__(NTHREADS)
         __syncthreads();
         {
             const float* AI = f.AINV + ch * BT * BT;
-            const float* QG = f.QG + ch * BT * D;
             tile_copy<BT, BT>([&](int r, int cc) { return ldg(AI + r * BT + cc); },
                               [&](int r, int cc, float x) { sA[r * LA + cc] = x; });
-            tile_copy<BT, D>([&](int r, int cc) { return ldg(QG + r * D + cc); },
-                             [&](int r, int cc, float x) { sM1[r * LD + cc] = x; });
         }
         __syncthreads();
         // P = A^T R_bar
@@ -189,16 +222,24 @@ __global__ void __launch_bounds__(NTHREADS)
 #pragma unroll
             for (int ii = 0; ii < 8; ++ii) P[(size_t)TR::row(ii) * D + v0 + TR::col(0)] = acc[ii][0];
         }
-        // S_bar = diag(lambda) S+bar + Q_g^T dO - W^T R_bar
-        {
-            float acc[D / 8][1], acc2[D / 8][1];
+        // S_bar = diag(lambda) S+bar + Q_g^T dO - W^T R_bar, one key block of rows at a time (Q_g
+        // and W through the one staging buffer)
+#pragma unroll 1
+        for (int kb = 0; kb < NKB; ++kb) {
+            float acc[DK / 8][1], acc2[DK / 8][1];
             zero(acc);
             zero(acc2);
-            tile_gemm_at<D, VT, D / 8, 1>(acc, sM1, LD, 0, BT, [&](int kk, int nn) { return sO[kk * LV + nn]; });
-            tile_gemm_at<D, VT, D / 8, 1>(acc2, sM2, LD, 0, BT, [&](int kk, int nn) { return sRb[kk * LV + nn]; });
+            __syncthreads();
+            stage(QG, kb);
+            __syncthreads();
+            tile_gemm_at<DK, VT, DK / 8, 1>(acc, sM, LD, 0, BT, [&](int kk, int nn) { return sO[kk * LV + nn]; });
+            __syncthreads();
+            stage(W, kb);
+            __syncthreads();
+            tile_gemm_at<DK, VT, DK / 8, 1>(acc2, sM, LD, 0, BT, [&](int kk, int nn) { return sRb[kk * LV + nn]; });
 #pragma unroll
-            for (int ii = 0; ii < D / 8; ++ii) {
-                const int m = TS::row(ii), nn = TS::col(0);
+            for (int ii = 0; ii < DK / 8; ++ii) {
+                const int m = kb * DK + TS::row(ii), nn = TS::col(0);
                 sSb[m * LV + nn] = sLam[m] * sSb[m * LV + nn] + acc[ii][0] - acc2[ii][0];
             }
         }
@@ -214,8 +255,8 @@ __global__ void __launch_bounds__(NTHREADS)
 
 template <typename TI, int D, int MODE>
 cudaError_t run_fwd(const Shape& s, const float* h0, Table t, Fwd f, void* o, float* ht, cudaStream_t st) {
-    constexpr int LD = D + 4, LV = VT + 1, LA = BT + 4;
-    constexpr size_t smem = sizeof(float) * (D * LV + BT * LD + BT * LV + BT * LA + D);
+    using SD = ScanDims<D>;
+    constexpr size_t smem = sizeof(float) * (D * SD::LV + BT * SD::LD + BT * SD::LV + BT * SD::LA + D);
     auto kern = k_fwd_scan<TI, D, MODE>;
     cudaError_t e = set_smem_once<k_fwd_scan<TI, D, MODE>>(smem);
     if (e != cudaSuccess) return e;
@@ -237,8 +278,8 @@ cudaError_t run_fwd_mode(int mode, const Shape& s, const float* h0, Table t, Fwd
 template <typename TI, int D>
 cudaError_t run_bwd(const Shape& s, const void* dout, const float* dht, Table t, Fwd f, Bwd b,
                     float* dh0, cudaStream_t st) {
-    constexpr int LD = D + 4, LV = VT + 1, LA = BT + 4;
-    constexpr size_t smem = sizeof(float) * (D * LV + 2 * BT * LD + 2 * BT * LV + BT * LA + D);
+    using SD = ScanDims<D>;
+    constexpr size_t smem = sizeof(float) * (D * SD::LV + BT * SD::LD + 2 * BT * SD::LV + BT * SD::LA + D);
     auto kern = k_bwd_scan<TI, D>;
     cudaError_t e = set_smem_once<k_bwd_scan<TI, D>>(smem);
     if (e != cudaSuccess) return e;

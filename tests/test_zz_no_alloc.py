@@ -34,6 +34,8 @@ def _noalloc(lib, p, o, ht):
 @pytest.mark.parametrize("kw", [
     dict(io="bf16", gate="channel", B=2, T=300, H=2, K=128, V=128),
     dict(io="fp32", gate="scalar", B=1, T=130, H=3, K=64, V=64),
+    dict(io="bf16", gate="channel", B=1, T=130, H=2, K=48, V=64),     # padded to 128
+    dict(io="bf16", gate="scalar", B=1, T=100, H=2, K=192, V=160),    # padded to 256
 ])
 def test_noalloc_forward_matches_allocating_forward_twice(kw):
     import chunkwise_delta_rule_gb300 as kda
