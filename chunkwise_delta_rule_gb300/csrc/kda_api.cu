@@ -90,8 +90,8 @@ Layout layout(const Dims& d) {
     Layout L;
     const size_t NC = (size_t)d.NC, H = (size_t)d.H, D = (size_t)d.D, BT = kda::BT;
     const size_t N = (size_t)d.N;
-    L.table = up(sizeof(int32_t) * NC) * 2 + up(sizeof(int32_t) * (N + 1)) + up(sizeof(int32_t) * N) * 2 +
-              up(sizeof(int32_t));
+    L.table = up(sizeof(int32_t) * NC) * 2 + up(sizeof(int32_t) * (N + 1)) + up(sizeof(int32_t) * N) * 3 +
+              up(sizeof(int32_t));   // the error word last (kda_device_status reads it there)
     const size_t chd = NC * H;
     L.fcore = up(4 * chd * BT * D) * 4 + up(4 * chd * BT * BT) * 2 + up(4 * chd * D);
     L.fextra = up(4 * chd * BT * D) + up(4 * chd * D * D);
@@ -123,6 +123,7 @@ kda::Table carve_table(Carver& c, const Dims& d) {
     t.seq_chunk0 = c.take<int32_t>(sizeof(int32_t) * (d.N + 1));
     t.seq_tok0 = c.take<int32_t>(sizeof(int32_t) * d.N);
     t.seq_len = c.take<int32_t>(sizeof(int32_t) * d.N);
+    t.seq_order = c.take<int32_t>(sizeof(int32_t) * d.N);
     t.err = c.take<int32_t>(sizeof(int32_t));
     return t;
 }

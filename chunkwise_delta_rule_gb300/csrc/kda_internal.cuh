@@ -42,8 +42,12 @@ struct Table {
     int32_t* seq_chunk0;  // [N+1] first chunk slot of each sequence
     int32_t* seq_tok0;    // [N] first token of each sequence
     int32_t* seq_len;     // [N] tokens of each sequence
+    int32_t* seq_order;   // [N] sequences by chunk count, most chunks first (ties by index; identity
+                          //     above ORDER_MAX sequences): the order the scans' CTAs take them in
     int32_t* err;         // [1] device error word
 };
+// Packed batches of up to this many sequences get their scans dispatched longest first.
+constexpr int ORDER_MAX = 256;
 
 // Forward chunk intermediates, fp32, one block per (chunk slot, head).
 struct Fwd {

@@ -23,6 +23,16 @@ constexpr int VT = 32;  // value columns per CTA
 // A operands of the products (W, Q_g, F, C_q, A) sit in rows of 16-byte aligned storage (DK + 4,
 // BT + 4) so that they are read four elements per load; the B operands (S, U/R, dO, R_bar) in
 // rows of VT + 1.
+// (sequence, head, value tile) of this CTA from its linear index over the grid (N, H, D / VT):
+// value tiles fastest, then heads, then sequences in the table's order (longest first).
+__device__ __forceinline__ void cta_unit(const Table& t, int H, int& nseq, int& h, int& v0) {
+    const int lin = (int)(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z));
+    const int nvt = (int)gridDim.z, rest = lin / nvt;
+    v0 = (lin - rest * nvt) * VT;
+    h = rest % H;
+    nseq = t.seq_order[rest / H];
+}
+
 template <int D>
 struct ScanDims {
     static constexpr int DK = D > 128 ? 128 : D;   // keys per staged block
@@ -43,8 +53,9 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     float* sA = sR + BT * LV;     // [BT][LA] C_q
     float* sLam = sA + BT * LA;   // [D]
 
-    const int nseq = blockIdx.x, h = blockIdx.y, v0 = blockIdx.z * VT, tid = threadIdx.x;
-    const int H = s.H;
+    const int H = s.H, tid = threadIdx.x;
+    int nseq, h, v0;
+    cta_unit(t, H, nseq, h, v0);
     const size_t st_off = ((size_t)nseq * H + h) * D * D;
     tile_copy<D, VT>([&](int r, int cc) { return h0 ? ldg(h0 + st_off + (size_t)r * D + v0 + cc) : 0.f; },
                      [&](int r, int cc, float x) { sS[r * LV + cc] = x; });
@@ -157,8 +168,9 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     float* sA = sRb + BT * LV;     // [BT][LA] C_q, then A
     float* sLam = sA + BT * LA;    // [D]
 
-    const int nseq = blockIdx.x, h = blockIdx.y, v0 = blockIdx.z * VT, tid = threadIdx.x;
-    const int H = s.H;
+    const int H = s.H, tid = threadIdx.x;
+    int nseq, h, v0;
+    cta_unit(t, H, nseq, h, v0);
     const size_t st_off = ((size_t)nseq * H + h) * D * D;
     tile_copy<D, VT>([&](int r, int cc) { return dht ? ldg(dht + st_off + (size_t)r * D + v0 + cc) : 0.f; },
                      [&](int r, int cc, float x) { sSb[r * LV + cc] = x; });

@@ -2,6 +2,10 @@
 // their chunk ranges, from cu_seqlens on the device (no host copy needed) or
 // from (B, T) for equal-length batches. Chunks restart at every sequence
 // start; the last chunk of a sequence holds the remainder (1..64 tokens).
+// It also ranks the sequences by chunk count: the state scans are serial over
+// a sequence's chunks, one CTA per (sequence, head), so dispatching the longest
+// sequences first keeps a packed batch's scans from ending on a long sequence
+// that started late (longest-processing-time-first list scheduling).
 #include "kda_internal.cuh"
 #include "tc.cuh"
 
@@ -69,6 +73,20 @@ __global__ void __launch_bounds__(TBL_THREADS) k_table(Shape s, int B, int T,
     }
     const int32_t total = min(s_cnt[TBL_THREADS - 1], s.NC);
     if (tid == 0) t.seq_chunk0[N] = total;
+    // rank = sequences with more chunks, or as many and a lower index (seq_len of every
+    // sequence is visible after the scan's barriers)
+    for (int n = tid; n < N; n += TBL_THREADS) {
+        int rank = n;
+        if (N <= ORDER_MAX) {
+            const int32_t cn = (t.seq_len[n] + BT - 1) / BT;
+            rank = 0;
+            for (int m = 0; m < N; ++m) {
+                const int32_t cm = (t.seq_len[m] + BT - 1) / BT;
+                rank += (cm > cn || (cm == cn && m < n)) ? 1 : 0;
+            }
+        }
+        t.seq_order[rank] = n;
+    }
     for (int slot = total + tid; slot < s.NC; slot += TBL_THREADS) {
         t.chunk_tok0[slot] = 0;
         t.chunk_len[slot] = 0;

@@ -388,7 +388,9 @@ __global__ void __launch_bounds__(ST_ALL, 1)
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tb = *tslot;
-    bscan_body(s, &tmo, dht, t, f, b, dh0, blockIdx.x, blockIdx.y, plo, pl, nullptr, base, tb);
+    // sequences in the table's order (longest first), every head of one before the next
+    const int lin = (int)(blockIdx.x + blockIdx.y * gridDim.x);
+    bscan_body(s, &tmo, dht, t, f, b, dh0, t.seq_order[lin / s.H], lin % s.H, plo, pl, nullptr, base, tb);
     tc::fence_before_sync();
     __syncthreads();
     if (threadIdx.x < 32) tc::tmem_dealloc(tb, 512);
@@ -1175,7 +1177,8 @@ __global__ void __launch_bounds__(CT, 1)
     tc::fence_after_sync();
     const uint32_t tb = *tslot;
     if ((int)blockIdx.x < s.N * s.H) {
-        bscan_body(s, &tmo, dht, t, f, bw, dh0, (int)blockIdx.x / s.H, (int)blockIdx.x % s.H, 0, 0, pc.flags, base, tb);
+        bscan_body(s, &tmo, dht, t, f, bw, dh0, t.seq_order[(int)blockIdx.x / s.H], (int)blockIdx.x % s.H, 0, 0,
+                   pc.flags, base, tb);
         tc::fence_async_smem();   // the scan's shared-memory writes before the consumer's tile loads land
         tc::fence_before_sync();
         __syncthreads();

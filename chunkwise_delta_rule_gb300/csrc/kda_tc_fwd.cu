@@ -857,7 +857,10 @@ __global__ void __launch_bounds__(ST_ALL, 1)
     uint64_t* full = bar + 4;                                        // operand stages 0, 1
     uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 6);
     const uint32_t sb = tc::smem_u32(base);
-    const int nseq = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5;
+    // (sequence, head) from the linear CTA index: sequences in the table's order, longest first,
+    // every head of one before the next
+    const int lin = (int)(blockIdx.x + blockIdx.y * gridDim.x);
+    const int nseq = t.seq_order[lin / s.H], h = lin % s.H, tid = threadIdx.x, warp = tid >> 5;
     const int c0 = t.seq_chunk0[nseq], c1 = t.seq_chunk0[nseq + 1];
     const bool issuer = warp == ST / 32;
     int filled = 0, waited = 0;   // bulk fills issued / consumed (issuer lane 0)

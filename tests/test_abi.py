@@ -57,7 +57,7 @@ def test_workspace_size_arithmetic():
     def up(x):
         return (x + 255) // 256 * 256
 
-    table = up(4 * NC) * 2 + up(4 * 3) + up(4 * 2) * 2 + up(4)
+    table = up(4 * NC) * 2 + up(4 * 3) + up(4 * 2) * 3 + up(4)
     chd = NC * H
     fcore = up(4 * chd * BT * D) * 4 + up(4 * chd * BT * BT) * 2 + up(4 * chd * D)
     fextra = up(4 * chd * BT * D) + up(4 * chd * D * D)
@@ -87,7 +87,7 @@ def test_workspace_size_arithmetic():
     # packed: chunk slots = ceil(T/64) + N
     pv = _prob(B=1, T=300, N=4, cu=0x2000, io=1)
     NCv = 5 + 4
-    tablev = up(4 * NCv) * 2 + up(4 * 5) + up(4 * 4) * 2 + up(4)
+    tablev = up(4 * NCv) * 2 + up(4 * 5) + up(4 * 4) * 3 + up(4)
     chv = NCv * 3
     assert _ws(pv, 0) == tablev + up(4 * chv * BT * D) * 4 + up(4 * chv * BT * BT) * 2 + up(4 * chv * D)
 
@@ -230,7 +230,7 @@ def test_unequal_widths_pad_to_the_working_width():
     assert _ws(wide, 1) == _ws(work, 1) + pad_b
     # K = V = 256 is a working width itself: its workspace is the chunk pipeline's (fp32 intermediates)
     NC, chd = 2 * 3, 2 * 3 * 3
-    table = 2 * up(4 * NC) + up(4 * 3) + 2 * up(4 * 2) + up(4)
+    table = 2 * up(4 * NC) + up(4 * 3) + 3 * up(4 * 2) + up(4)
     fcore = 4 * up(4 * chd * 64 * D) + 2 * up(4 * chd * 64 * 64) + up(4 * chd * D)
     assert _ws(work, 0) == table + fcore
 
