@@ -89,22 +89,23 @@ def test_small_cases_match_oracle(kw):
     compare_full(case, got, ref, TOL[case.io])
 
 
-@pytest.mark.parametrize("io", ["fp32", "bf16"])
-def test_packed_sequences(io):
-    # one-token, exactly-one-chunk, one-past-a-chunk, two-chunk and ragged sequences
-    case = make_case(io=io, gate="channel", B=1, H=2, K=64, V=64, seed=31,
+@pytest.mark.parametrize("io,K", [("fp32", 64), ("bf16", 64), ("bf16", 48)])
+def test_packed_sequences(io, K):
+    # one-token, exactly-one-chunk, one-past-a-chunk, two-chunk and ragged sequences (bf16 at
+    # widths below 128 runs zero-padded on the tensor-core path)
+    case = make_case(io=io, gate="channel", B=1, H=2, K=K, V=64, seed=31,
                      lengths=[1, 64, 65, 130, 3, 200])
     got = packed_np(case, gpu_run(case))
     compare_full(case, got, run_oracle(case), TOL[io])
 
 
-@pytest.mark.parametrize("io,D", [("fp32", 64), ("bf16", 128)])
+@pytest.mark.parametrize("io,D", [("fp32", 64), ("bf16", 128), ("bf16", 64)])
 @pytest.mark.parametrize("gate", ["channel", "scalar"])
 def test_strong_decay_takes_the_subchunk_path(gate, io, D):
     """g around -4: the in-chunk gate range exceeds the single-anchor and
     centering thresholds, so the 16-token anchored paths run (the CUDA-core
-    prep of wide chunks on the tensor-core path); they must stay within the
-    I/O dtype's tolerance."""
+    prep of wide chunks on the tensor-core path, which bf16 at 64 reaches
+    zero-padded to 128); they must stay within the I/O dtype's tolerance."""
     case = make_case(io=io, gate=gate, B=1, T=200, H=2, K=D, V=D, seed=5, g_shift=-4.0,
                      g_min=-8.0)
     g = case.g if gate == "channel" else case.g[..., None]
