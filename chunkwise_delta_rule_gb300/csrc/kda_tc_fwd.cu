@@ -508,7 +508,9 @@ constexpr int NB_C = 3;            //                compute warps only
 //                           images for the TMA stores
 //   mode 2 (S, R):          stage = W [64][128] (16 KB), F; S and R tile images of two chunks
 //   mode 3 (output, S, R):  stage as mode 1; S and R of one chunk; outputs stored from registers
-// S and R go to HBM by one bulk copy each.
+// S and R go to HBM by one bulk copy each. Every mode also holds one fp32 U tile [64][128] (32 KB),
+// bulk-copied by the issuer a chunk ahead (it replaced per-thread loads of U through L1, whose
+// latency sat on the chunk's critical chain).
 template <int MODE>
 struct ScanMap {
     static constexpr bool OUT = (MODE & 1) != 0;
@@ -521,7 +523,8 @@ struct ScanMap {
     static constexpr int OST = 2 * STG;
     static constexpr int HST = OST + NOST * BT * D * 2;         // S [128][128] bf16 each
     static constexpr int RST = HST + NSR * D * D * 2;           // R [64][128] bf16 each
-    static constexpr int LAM = RST + NSR * BT * D * 2;
+    static constexpr int UST = RST + NSR * BT * D * 2;          // U [64][128] fp32
+    static constexpr int LAM = UST + BT * D * 4;
     static constexpr int TST = LAM + 512;
     static constexpr int BAR = TST + 8 * 1280;
     static constexpr int SMEM = BAR + 64 + 1024;
@@ -615,6 +618,7 @@ __device__ __forceinline__ void fscan_compute(const Shape& s, const float* __res
     const int vcol = 32 * quad + lane;  // TMEM lane and value column of this thread
     const uint32_t tl = tc::taddr(tb, 32 * quad, 0);
     const size_t st_off = ((size_t)nseq * H + h) * D * D;
+    uint64_t* ufull = bar + 7;          // the U tile of the current chunk has landed
     const int kb = 64 * half;   // this thread's half of the key columns of S^T
     const int ib = 32 * half;   // this thread's half of the chunk rows
 
@@ -643,11 +647,6 @@ __device__ __forceinline__ void fscan_compute(const Shape& s, const float* __res
     for (int c = c0; c < c1; ++c) {
         const int it = c - c0, stage = it & 1;
         const size_t ch = (size_t)c * H + h;
-        // U rows of this thread's value column (consumed in the R pass)
-        float u[32];
-        const float* U = f.U + ch * BT * D + (size_t)ib * D + vcol;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) u[i] = __ldg(U + (size_t)i * D);
         if (tid < D) sLam[tid] = exp2f(gln);
         if (c + 1 < c1 && tid < D) gln = __ldg(f.GL + (ch + H) * D + tid);
         if (it > 0) wait_one(&bar[1], (it - 1) & 1);   // the state update of chunk c-1
@@ -682,6 +681,14 @@ __device__ __forceinline__ void fscan_compute(const Shape& s, const float* __res
             tc::tmem_st16(tl + cb, a);
         }
         tc::tmem_wait_st();
+        // U rows of this thread's value column (staged by the issuer a chunk ahead)
+        float u[32];
+        wait_one(ufull, it & 1);
+        {
+            const float* sU = reinterpret_cast<const float*>(base + ScanMap<MODE>::UST) + ib * D + vcol;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) u[i] = sU[i * D];
+        }
         // 3. R^T = U^T - D1 -> bf16 A operand (TMEM) of the state update and the output
         wait_one(&bar[0], it & 1);
         uint32_t rp[16];   // R^T rows ib.. of this value column, bf16 pairs (kept for the saved R)
@@ -843,6 +850,11 @@ __device__ __forceinline__ void fscan_issue(const Shape& s, const Table& t, cons
             for (int ks = 0; ks < 4; ++ks) tc::mma_bf16_ts_w(tD + 64, aR + 8 * ks, tc::kstep_k(dA, BT, ks), i64, 1);
             tc::mma_commit_w(&bar[2 + stage]);
         }
+        // U of chunk c+1: the compute warps read this chunk's U before the R hand-over above
+        if (lane == 0 && c + 1 < c1) {
+            tc::mbar_arrive_expect_tx(bar + 7, BT * D * 4);
+            tc::bulk_g2s(sb + ScanMap<MODE>::UST, f.U + ((size_t)(c + 1) * H + h) * BT * D, BT * D * 4, bar + 7);
+        }
     }
 }
 
@@ -868,10 +880,13 @@ __global__ void __launch_bounds__(ST_ALL, 1)
 
     if (issuer && (tid & 31) == 0) {
         for (int i = 0; i < 6; ++i) tc::mbar_init(&bar[i], 1);
+        tc::mbar_init(&bar[7], 1);   // U tile (bar + 6 holds the TMEM slot)
         tc::fence_mbar_init();
         if (c0 < c1) {
             fscan_fill<MODE>(sb, f, (size_t)c0 * s.H + h, &full[0]);
             filled = 1;
+            tc::mbar_arrive_expect_tx(&bar[7], BT * D * 4);
+            tc::bulk_g2s(sb + ScanMap<MODE>::UST, f.U + ((size_t)c0 * s.H + h) * BT * D, BT * D * 4, &bar[7]);
         }
     }
     if (warp == 0) {
@@ -886,9 +901,12 @@ __global__ void __launch_bounds__(ST_ALL, 1)
         fscan_issue<MODE>(s, t, f, &tmo, sb, bar, full, tb, h, c0, c1, pl, pt, filled, waited);
     else
         fscan_compute<MODE>(s, h0, t, f, o, ht, base, bar, tb, nseq, h, c0, c1);
-    // a bulk fill still in flight (only after a timeout) lands before the CTA leaves
-    if (issuer && (tid & 31) == 0)
+    // a bulk fill still in flight (only after a timeout) lands before the CTA leaves; the last U
+    // tile (chunk c1-1, parity of its chunk index) likewise
+    if (issuer && (tid & 31) == 0) {
         for (; waited < filled; ++waited) tc::mbar_wait(&full[waited & 1], (waited >> 1) & 1);
+        if (c1 > c0) tc::mbar_wait(&bar[7], (c1 - 1 - c0) & 1);
+    }
     tc::fence_before_sync();
     __syncthreads();
     // S and R of the last chunk (staged after the issuer's loop ended)
