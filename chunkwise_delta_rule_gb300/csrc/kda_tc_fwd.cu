@@ -527,7 +527,7 @@ struct ScanMap {
     static constexpr int LAM = UST + BT * D * 4;
     static constexpr int TST = LAM + 512;
     static constexpr int BAR = TST + 8 * 1280;
-    static constexpr int SMEM = BAR + 64 + 1024;
+    static constexpr int SMEM = BAR + 128 + 1024;
     static_assert(SMEM <= 232448, "scan shared memory above the per-block limit");
     static_assert(OST % 1024 == 0, "swizzled TMA stores need 1024-byte aligned tiles");
 };
@@ -709,11 +709,24 @@ __device__ __forceinline__ void fscan_compute(const Shape& s, const float* __res
         tc::tmem_wait_st();
         tc::fence_before_sync();
         tc::named_sync(NB_AR, ST_ALL);
-        // 4. while the state update runs: the saved S and R, the output of chunk c-1 (one output
-        //    barrier per TMEM buffer, so the commit of this chunk's output cannot be taken for it)
+        // 4. while the state update runs: the output of chunk c-1 (one output barrier per TMEM
+        //    buffer, so the commit of this chunk's output cannot be taken for it), then the saved S
+        //    and R (mode 3: once the issuer reports the single staging pair read out by the bulk
+        //    copy of the previous chunk's)
+        if ((MODE & 1) && it > 0) {
+            // output of chunk c-1: a full chunk goes to staging tile (it-1)&1 (stored by the
+            // issuer after the next hand-over), a tail chunk straight to HBM
+            wait_one(&bar[2 + ((it - 1) & 1)], ((it - 1) >> 1) & 1);
+            const uint32_t to = tl + T_DO + 128 * ((it - 1) & 1) + 64;
+            if (MODE == 1 && lenp == BT)
+                fscan_stage_out(to, reinterpret_cast<bf16*>(base + ScanMap<MODE>::OST) + ((it - 1) & 1) * BT * D, ib, vcol);
+            else
+                fscan_store_tail(to, lenp, tok0p, H, h, ib, quad, lane, tst, o);
+        }
         if (MODE & 2) {
             // R and S (from the bf16 S^T operand still in TMEM) as tile images into their staging
             // buffer; the issuer copies them to HBM after the next hand-over
+            if (ScanMap<MODE>::NSR == 1) wait_one(bar + 8, it & 1);
             const int sbuf = (ScanMap<MODE>::NSR == 2) ? (it & 1) : 0;
             uint16_t* hs = reinterpret_cast<uint16_t*>(base + ScanMap<MODE>::HST) + sbuf * D * D;
             uint16_t* rs = reinterpret_cast<uint16_t*>(base + ScanMap<MODE>::RST) + sbuf * BT * D;
@@ -730,16 +743,6 @@ __device__ __forceinline__ void fscan_compute(const Shape& s, const float* __res
                 for (int j = 0; j < 32; ++j) hs[tile_el(D, kb + 32 * hq + j, vcol)] = p16[j];
             }
             tc::fence_async_smem();
-        }
-        if ((MODE & 1) && it > 0) {
-            // output of chunk c-1: a full chunk goes to staging tile (it-1)&1 (stored by the
-            // issuer after the next hand-over), a tail chunk straight to HBM
-            wait_one(&bar[2 + ((it - 1) & 1)], ((it - 1) >> 1) & 1);
-            const uint32_t to = tl + T_DO + 128 * ((it - 1) & 1) + 64;
-            if (MODE == 1 && lenp == BT)
-                fscan_stage_out(to, reinterpret_cast<bf16*>(base + ScanMap<MODE>::OST) + ((it - 1) & 1) * BT * D, ib, vcol);
-            else
-                fscan_store_tail(to, lenp, tok0p, H, h, ib, quad, lane, tst, o);
         }
         lenp = __ldg(t.chunk_len + c);
         tok0p = __ldg(t.chunk_tok0 + c);
@@ -828,12 +831,7 @@ __device__ __forceinline__ void fscan_issue(const Shape& s, const Table& t, cons
         // the staging tiles stored during chunk c-1 are rewritten after this hand-over; the output
         // tile stored just now may still be read (it is rewritten during chunk c+1), and so may a
         // double-buffered S/R pair; a single S/R pair is rewritten after this hand-over
-        if (lane == 0) {
-            if (ScanMap<MODE>::NSR == 1)
-                tc::bulk_wait_read();
-            else
-                tc::bulk_wait_read_prev();
-        }
+        if (lane == 0 && ScanMap<MODE>::NSR != 1) tc::bulk_wait_read_prev();
         __syncwarp();
         tc::named_sync(NB_AR, ST_ALL);
         tc::fence_after_sync();
@@ -849,6 +847,13 @@ __device__ __forceinline__ void fscan_issue(const Shape& s, const Table& t, cons
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) tc::mma_bf16_ts_w(tD + 64, aR + 8 * ks, tc::kstep_k(dA, BT, ks), i64, 1);
             tc::mma_commit_w(&bar[2 + stage]);
+        }
+        // a single S/R staging pair (mode 3) is rewritten by the compute warps during this chunk:
+        // report it free once the bulk copy of the previous chunk's pair has read it (waiting here,
+        // after the MMAs are issued, keeps the copy off the chain)
+        if (ScanMap<MODE>::NSR == 1 && lane == 0) {
+            tc::bulk_wait_read();
+            tc::mbar_arrive(bar + 8);
         }
         // U of chunk c+1: the compute warps read this chunk's U before the R hand-over above
         if (lane == 0 && c + 1 < c1) {
@@ -881,6 +886,7 @@ __global__ void __launch_bounds__(ST_ALL, 1)
     if (issuer && (tid & 31) == 0) {
         for (int i = 0; i < 6; ++i) tc::mbar_init(&bar[i], 1);
         tc::mbar_init(&bar[7], 1);   // U tile (bar + 6 holds the TMEM slot)
+        tc::mbar_init(&bar[8], 1);   // mode 3: the S/R staging pair is free
         tc::fence_mbar_init();
         if (c0 < c1) {
             fscan_fill<MODE>(sb, f, (size_t)c0 * s.H + h, &full[0]);
