@@ -104,12 +104,12 @@ def kernel_work(case, save=False):
         fl["k_fwd_scan_tc_save"] += 4 * n * d * d
         fl["k_bwd_scan_tc"] += 6 * n * d * d + 4 * n * n * d
         fl["k_bwd_consumer_tc"] += 12 * n * n * d + 6 * n * d * d
-        # tensor-core path: bf16 tiles W, F, Q_g, C_q, A, S, S+bar, R, P; fp32 U and G at the chunk end
-        by["k_prep_tc"] += (3 * n * d * e + n * gb + n * e + 3 * n * d * 2 + n * n * 2 + n * d * 4 + d * 4
+        # tensor-core path: bf16 tiles W, U, F, Q_g, C_q, A, S, S+bar, R, P; fp32 G at the chunk end
+        by["k_prep_tc"] += (3 * n * d * e + n * gb + n * e + 4 * n * d * 2 + n * n * 2 + d * 4
                             + (n * n * 2 if save else 0))
-        by["k_fwd_scan_tc"] += 3 * n * d * 2 + n * n * 2 + n * d * 4 + d * 4 + n * d * e
-        by["k_fwd_scan_tc_recompute"] += 2 * n * d * 2 + n * d * 4 + d * 4 + d * d * 2 + n * d * 2
-        by["k_fwd_scan_tc_save"] += 2 * n * d * 2 + n * d * 4 + d * 4 + d * d * 2 + n * d * 2
+        by["k_fwd_scan_tc"] += 4 * n * d * 2 + n * n * 2 + d * 4 + n * d * e
+        by["k_fwd_scan_tc_recompute"] += 3 * n * d * 2 + d * 4 + d * d * 2 + n * d * 2
+        by["k_fwd_scan_tc_save"] += 3 * n * d * 2 + d * 4 + d * d * 2 + n * d * 2
         by["k_bwd_scan_tc"] += 3 * n * d * 2 + 2 * n * n * 2 + d * 4 + n * d * e + d * d * 2 + n * d * 2
         by["k_bwd_consumer_tc"] += (3 * n * d * 2 + 2 * d * d * 2 + 3 * n * d * e + n * gb + n * e
                                     + 3 * n * d * e + n * e + n * gb)

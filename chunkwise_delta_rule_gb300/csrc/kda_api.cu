@@ -97,8 +97,7 @@ Layout layout(const Dims& d) {
     L.fextra = up(4 * chd * BT * D) + up(4 * chd * D * D);
     L.bwd = up(4 * chd * BT * D) * 4 + up(4 * chd * D * D) + up(4 * chd * BT * BT) * 2 +
             up(4 * chd * D) + up(4 * chd * BT);
-    L.ftc = up(2 * chd * BT * D) * 3 + up(2 * chd * BT * BT) + up(4 * chd * BT * D) + up(4 * chd * D) +
-            up(4 * chd) + up(4 * (chd + 1));
+    L.ftc = up(2 * chd * BT * D) * 4 + up(2 * chd * BT * BT) + up(4 * chd * D) + up(4 * chd) + up(4 * (chd + 1));
     L.ftc_b = up(2 * chd * BT * BT) + up(2 * chd * D * D) + up(2 * chd * BT * D);
     L.btc = up(2 * chd * D * D) + up(2 * chd * BT * D);
     L.wscr = up(4 * chd * BT * D) * 3 + up(4 * chd * BT * BT) * 2 + up(4 * chd * D) + up(4 * chd * BT);
@@ -166,7 +165,7 @@ void carve_fwd_tc(Carver& c, const Dims& d, kda::FwdTC& f, bool bwd_arrays) {
     f.KG = c.take<__nv_bfloat16>(2 * chd * BT * D);
     f.QG = c.take<__nv_bfloat16>(2 * chd * BT * D);
     f.AQK = c.take<__nv_bfloat16>(2 * chd * BT * BT);
-    f.U = c.take<float>(4 * chd * BT * D);
+    f.U = c.take<__nv_bfloat16>(2 * chd * BT * D);
     f.GL = c.take<float>(4 * chd * D);
     f.WIDE = c.take<int32_t>(4 * chd);
     f.WLIST = c.take<int32_t>(4 * (chd + 1));

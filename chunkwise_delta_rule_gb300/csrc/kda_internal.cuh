@@ -83,7 +83,7 @@ struct FwdTC {
     __nv_bfloat16* KG;    // [NC,H,BT,D]  F (keys decayed to the chunk end)
     __nv_bfloat16* QG;    // [NC,H,BT,D]  Q_g
     __nv_bfloat16* AQK;   // [NC,H,BT,BT] C_q, rows = receiving token i
-    float* U;             // [NC,H,BT,D]  U = A Z
+    __nv_bfloat16* U;     // [NC,H,BT,D]  U = A Z, rows = chunk tokens (bf16, as the other WY factors)
     float* GL;            // [NC,H,D]     cumulative log2-decay at the last token
     int32_t* WIDE;        // [NC,H]       1: gate range too wide for one anchor
     int32_t* WLIST;       // [1 + NC*H]   count, then chunk slot * H + head of every WIDE chunk

@@ -228,11 +228,17 @@ __device__ __forceinline__ void prep_chunk(int c, int h, const Shape& s, const T
             float acc[8][TN];
             zero(acc);
             tile_gemm_ar<BT, DC, 8, TN>(acc, sAi, LA, 0, BT, [&](int kk, int nn) { return sQ[kk * LD + nn]; });
-            float* U = (TCOUT ? ft.U : f.U) + ch * BT * D;
 #pragma unroll
             for (int ii = 0; ii < 8; ++ii)
 #pragma unroll
-                for (int jj = 0; jj < TN; ++jj) U[TM8::row(ii) * D + c0 + TM8::col(jj)] = acc[ii][jj];
+                for (int jj = 0; jj < TN; ++jj) {
+                    const size_t o = ch * BT * D + TM8::row(ii) * D + c0 + TM8::col(jj);
+                    if (TCOUT) {
+                        ft.U[o] = __float2bfloat16_rn(acc[ii][jj]);
+                    } else {
+                        f.U[o] = acc[ii][jj];
+                    }
+                }
         }
     }
 }

@@ -467,15 +467,15 @@ __global__ void __launch_bounds__(PT, 2)
                     for (int jj = 0; jj < 16; ++jj) sW[(cb + jj) * LW + row] = __float2bfloat16_rn(a[jj] * c2);
                 }
             } else {
-                // U^T row = value `row` -> U[i][row] (fp32, coalesced over the value index)
-                float* U = f.U + ch * BT * D + row;
+                // U^T row = value `row` -> U[i][row] (bf16, coalesced over the value index)
+                bf16* U = f.U + ch * BT * D + row;
 #pragma unroll
                 for (int cb = 0; cb < BT; cb += 16) {
                     float a[16];
                     tc::tmem_ld16(tc::taddr(tb + 128, 32 * (warp & 3), cb), a);
                     tc::tmem_wait_ld();
 #pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) U[(size_t)(cb + jj) * D] = a[jj];
+                    for (int jj = 0; jj < 16; ++jj) U[(size_t)(cb + jj) * D] = __float2bfloat16_rn(a[jj]);
                 }
             }
             __syncthreads();
@@ -508,9 +508,8 @@ constexpr int NB_C = 3;            //                compute warps only
 //                           images for the TMA stores
 //   mode 2 (S, R):          stage = W [64][128] (16 KB), F; S and R tile images of two chunks
 //   mode 3 (output, S, R):  stage as mode 1; S and R of one chunk; outputs stored from registers
-// S and R go to HBM by one bulk copy each. Every mode also holds one fp32 U tile [64][128] (32 KB),
-// bulk-copied by the issuer a chunk ahead (it replaced per-thread loads of U through L1, whose
-// latency sat on the chunk's critical chain).
+// S and R go to HBM by one bulk copy each. Every mode also holds one bf16 U tile [64][128] (16 KB,
+// row-major), bulk-copied by the issuer a chunk ahead.
 template <int MODE>
 struct ScanMap {
     static constexpr bool OUT = (MODE & 1) != 0;
@@ -523,8 +522,8 @@ struct ScanMap {
     static constexpr int OST = 2 * STG;
     static constexpr int HST = OST + NOST * BT * D * 2;         // S [128][128] bf16 each
     static constexpr int RST = HST + NSR * D * D * 2;           // R [64][128] bf16 each
-    static constexpr int UST = RST + NSR * BT * D * 2;          // U [64][128] fp32
-    static constexpr int LAM = UST + BT * D * 4;
+    static constexpr int UST = RST + NSR * BT * D * 2;          // U [64][128] bf16
+    static constexpr int LAM = UST + BT * D * 2;
     static constexpr int TST = LAM + 512;
     static constexpr int BAR = TST + 8 * 1280;
     static constexpr int SMEM = BAR + 128 + 1024;
@@ -685,9 +684,9 @@ __device__ __forceinline__ void fscan_compute(const Shape& s, const float* __res
         float u[32];
         wait_one(ufull, it & 1);
         {
-            const float* sU = reinterpret_cast<const float*>(base + ScanMap<MODE>::UST) + ib * D + vcol;
+            const bf16* sU = reinterpret_cast<const bf16*>(base + ScanMap<MODE>::UST) + ib * D + vcol;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) u[i] = sU[i * D];
+            for (int i = 0; i < 32; ++i) u[i] = __bfloat162float(sU[i * D]);
         }
         // 3. R^T = U^T - D1 -> bf16 A operand (TMEM) of the state update and the output
         wait_one(&bar[0], it & 1);
@@ -857,8 +856,8 @@ __device__ __forceinline__ void fscan_issue(const Shape& s, const Table& t, cons
         }
         // U of chunk c+1: the compute warps read this chunk's U before the R hand-over above
         if (lane == 0 && c + 1 < c1) {
-            tc::mbar_arrive_expect_tx(bar + 7, BT * D * 4);
-            tc::bulk_g2s(sb + ScanMap<MODE>::UST, f.U + ((size_t)(c + 1) * H + h) * BT * D, BT * D * 4, bar + 7);
+            tc::mbar_arrive_expect_tx(bar + 7, BT * D * 2);
+            tc::bulk_g2s(sb + ScanMap<MODE>::UST, f.U + ((size_t)(c + 1) * H + h) * BT * D, BT * D * 2, bar + 7);
         }
     }
 }
@@ -891,8 +890,8 @@ __global__ void __launch_bounds__(ST_ALL, 1)
         if (c0 < c1) {
             fscan_fill<MODE>(sb, f, (size_t)c0 * s.H + h, &full[0]);
             filled = 1;
-            tc::mbar_arrive_expect_tx(&bar[7], BT * D * 4);
-            tc::bulk_g2s(sb + ScanMap<MODE>::UST, f.U + ((size_t)c0 * s.H + h) * BT * D, BT * D * 4, &bar[7]);
+            tc::mbar_arrive_expect_tx(&bar[7], BT * D * 2);
+            tc::bulk_g2s(sb + ScanMap<MODE>::UST, f.U + ((size_t)c0 * s.H + h) * BT * D, BT * D * 2, &bar[7]);
         }
     }
     if (warp == 0) {

@@ -65,8 +65,8 @@ def test_workspace_size_arithmetic():
     assert _ws(p, 0) == table + fcore
     assert _ws(p, 1) == table + fcore + fextra + bwd
     ptc = _prob(io=0)
-    ftc = (up(2 * chd * BT * D) * 3 + up(2 * chd * BT * BT) + up(4 * chd * BT * D) + up(4 * chd * D) + up(4 * chd)
-           + up(4 * (chd + 1)))
+    # bf16 W, F, Q_g, U tiles, C_q; fp32 gate at the chunk end; wide flags and list
+    ftc = up(2 * chd * BT * D) * 4 + up(2 * chd * BT * BT) + up(4 * chd * D) + up(4 * chd) + up(4 * (chd + 1))
     assert _ws(ptc, 0) == table + ftc
     ftc_b = up(2 * chd * BT * BT) + up(2 * chd * D * D) + up(2 * chd * BT * D)
     btc = up(2 * chd * D * D) + up(2 * chd * BT * D)
