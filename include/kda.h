@@ -190,7 +190,7 @@ kda_status kda_chunk_bwd(const kda_problem *p, const void *dout, const float *dh
  * KDA_NOALLOC_SCRATCH_BYTES (32 MiB) that every device loading the library
  * holds until the process exits. The entry point itself allocates nothing.
  * - Size limit: problems with kda_workspace_size(p, 0) above the array's size
- *   (at K = V = 128 about 370 chunk x head units with bf16 I/O, about 200
+ *   (at K = V = 128 about 450 chunk x head units with bf16 I/O, about 200
  *   with fp32 I/O) are rejected with
  *   KDA_ERR_WORKSPACE before anything is enqueued; save_policy must be 0.
  * - Set-up: the first call on each device, with that device current, looks up
