@@ -507,7 +507,7 @@ constexpr int NB_C = 3;            //                compute warps only
 //                           (16 KB, read MN-major), C_q [64][64] (8 KB); two [64][128] output tile
 //                           images for the TMA stores
 //   mode 2 (S, R):          stage = W [64][128] (16 KB), F; S and R tile images of two chunks
-//   mode 3 (output, S, R):  stage as mode 1; S and R of one chunk; outputs stored from registers
+//   mode 3 (output, S, R):  stage and output tiles as mode 1; S and R of one chunk
 // S and R go to HBM by one bulk copy each. Every mode also holds one bf16 U tile [64][128] (16 KB,
 // row-major), bulk-copied by the issuer a chunk ahead.
 template <int MODE>
@@ -517,7 +517,7 @@ struct ScanMap {
     static constexpr int KG = WROWS * D * 2;                    // F
     static constexpr int AQ = KG + BT * D * 2;                  // C_q (output modes)
     static constexpr int STG = OUT ? AQ + BT * BT * 2 : AQ;     // bytes of one stage
-    static constexpr int NOST = (MODE == 1) ? 2 : 0;            // output staging tiles
+    static constexpr int NOST = (MODE & 1) ? 2 : 0;             // output staging tiles
     static constexpr int NSR = (MODE == 2) ? 2 : (MODE == 3) ? 1 : 0;   // S/R staging pairs
     static constexpr int OST = 2 * STG;
     static constexpr int HST = OST + NOST * BT * D * 2;         // S [128][128] bf16 each
@@ -717,7 +717,7 @@ __device__ __forceinline__ void fscan_compute(const Shape& s, const float* __res
             // issuer after the next hand-over), a tail chunk straight to HBM
             wait_one(&bar[2 + ((it - 1) & 1)], ((it - 1) >> 1) & 1);
             const uint32_t to = tl + T_DO + 128 * ((it - 1) & 1) + 64;
-            if (MODE == 1 && lenp == BT)
+            if ((MODE & 1) && lenp == BT)
                 fscan_stage_out(to, reinterpret_cast<bf16*>(base + ScanMap<MODE>::OST) + ((it - 1) & 1) * BT * D, ib, vcol);
             else
                 fscan_store_tail(to, lenp, tok0p, H, h, ib, quad, lane, tst, o);
@@ -753,7 +753,7 @@ __device__ __forceinline__ void fscan_compute(const Shape& s, const float* __res
             // the last output: staging tile last&1 (stored by the issuer at the end) or HBM
             wait_one(&bar[2 + (last & 1)], (last >> 1) & 1);
             const uint32_t to = tl + T_DO + 128 * (last & 1) + 64;
-            if (MODE == 1 && lenp == BT)
+            if ((MODE & 1) && lenp == BT)
                 fscan_stage_out(to, reinterpret_cast<bf16*>(base + ScanMap<MODE>::OST) + (last & 1) * BT * D, ib, vcol);
             else
                 fscan_store_tail(to, lenp, tok0p, H, h, ib, quad, lane, tst, o);
@@ -821,9 +821,9 @@ __device__ __forceinline__ void fscan_issue(const Shape& s, const Table& t, cons
             tc::bulk_commit();
         }
         // the output of chunk c-2 (a full chunk), staged by the compute warps during chunk c-1
-        const bool o_out = MODE == 1 && it >= 2 && pl == BT;
+        const bool o_out = (MODE & 1) && it >= 2 && pl == BT;
         if (o_out) fscan_tma_out(tmo, sb + ScanMap<MODE>::OST + (it & 1) * BT * D * 2, pt, h, lane);
-        if (MODE == 1 && it >= 1) {   // extent of chunk c-1, whose output is stored next iteration
+        if ((MODE & 1) && it >= 1) {   // extent of chunk c-1, whose output is stored next iteration
             pl = __ldg(t.chunk_len + c - 1);
             pt = __ldg(t.chunk_tok0 + c - 1);
         }
@@ -925,7 +925,7 @@ __global__ void __launch_bounds__(ST_ALL, 1)
         tc::bulk_wait_all();
     }
     // the last two outputs (staged after the issuer's loop ended)
-    if (MODE == 1 && issuer && c1 > c0) {
+    if ((MODE & 1) && issuer && c1 > c0) {
         const int last = c1 - 1 - c0, lane = tid & 31;
         constexpr int OST = ScanMap<MODE>::OST;
         if (last >= 1 && pl == BT) fscan_tma_out(&tmo, sb + OST + ((last - 1) & 1) * BT * D * 2, pt, h, lane);
@@ -959,7 +959,7 @@ cudaError_t run_scan(const Shape& s, const float* h0, Table t, FwdTC f, void* o,
     if (e != cudaSuccess) return e;
     CUtensorMap mo;
     memset(&mo, 0, sizeof(mo));
-    if (MODE == 1 && !tmap_rows_bf16(&mo, o, s.Ttot, s.H, D)) return cudaErrorInvalidValue;
+    if ((MODE & 1) && !tmap_rows_bf16(&mo, o, s.Ttot, s.H, D)) return cudaErrorInvalidValue;
     dim3 grid(s.N, s.H);
     k_fwd_scan_tc<MODE><<<grid, ST_ALL, ScanMap<MODE>::SMEM, st>>>(s, mo, h0, t, f, (bf16*)o, ht);
     return cudaGetLastError();
