@@ -20,8 +20,10 @@ constexpr size_t ALIGN = 256;
 size_t up(size_t x) { return (x + ALIGN - 1) / ALIGN * ALIGN; }
 
 struct Dims {
-    int N = 0, NC = 0, Ttot = 0, D = 0, H = 0;
-    int per = 0;   // chunks per sequence of an equal-length batch (0: packed sequences)
+    int N = 0, NC = 0, Ttot = 0, H = 0;
+    int D = 0, V = 0;   // key and value widths of the problem
+    int WD = 0;         // working width of the chunk intermediates (the tile width of the path)
+    int per = 0;        // chunks per sequence of an equal-length batch (0: packed sequences)
 };
 
 // Value widths above the block width (128; 256 when K > 128) run as value blocks.
@@ -59,6 +61,10 @@ kda_status check_dims(const kda_problem* p, Dims& d) {
     if (tok > 0x7fffffffLL / 2) return fail(KDA_ERR_UNSUPPORTED, "too many tokens");
     d.Ttot = (int)tok;
     d.D = p->K;
+    d.V = p->V;
+    // bf16 up to 128 wide runs on the tensor cores at 128; otherwise the width itself (the
+    // CUDA-core path's problems are padded to K = V = 64, 128 or 256 before they get here)
+    d.WD = (p->io == KDA_BF16 && p->K <= 128 && p->V <= 128) ? 128 : p->K;
     d.H = p->H;
     const long long per = (p->T + kda::BT - 1) / kda::BT;
     if (p->cu_seqlens) {
@@ -82,13 +88,14 @@ struct Layout {
     size_t piece = 0;   // time pieces of the tensor-core backward: two state adjoints, the claim counters
 };
 
-// The tensor-core path serves bf16 I/O at K = V = 128 (narrower bf16 widths reach it padded);
-// everything else runs the fp32 CUDA-core kernels.
-bool use_tc(const kda_problem* p) { return p->io == KDA_BF16 && p->K == 128; }
+// The tensor-core path serves bf16 I/O with K, V <= 128 (at 128, its tile width: widths that are
+// multiples of 8 are read and written as they are, others arrive padded to 128); everything else
+// runs the fp32 CUDA-core kernels.
+bool use_tc(const kda_problem* p) { return p->io == KDA_BF16 && p->K <= 128 && p->V <= 128; }
 
 Layout layout(const Dims& d) {
     Layout L;
-    const size_t NC = (size_t)d.NC, H = (size_t)d.H, D = (size_t)d.D, BT = kda::BT;
+    const size_t NC = (size_t)d.NC, H = (size_t)d.H, D = (size_t)d.WD, BT = kda::BT;
     const size_t N = (size_t)d.N;
     L.table = up(sizeof(int32_t) * NC) * 2 + up(sizeof(int32_t) * (N + 1)) + up(sizeof(int32_t) * N) * 3 +
               up(sizeof(int32_t));   // the error word last (kda_device_status reads it there)
@@ -101,7 +108,7 @@ Layout layout(const Dims& d) {
     L.ftc_b = up(2 * chd * BT * BT) + up(2 * chd * D * D) + up(2 * chd * BT * D);
     L.btc = up(2 * chd * D * D) + up(2 * chd * BT * D);
     L.wscr = up(4 * chd * BT * D) * 3 + up(4 * chd * BT * BT) * 2 + up(4 * chd * D) + up(4 * chd * BT);
-    if (d.per) L.piece = 2 * up(4 * N * H * D * D) + up(4 * kda::MAX_PIECES) + up(4 * chd);
+    if (d.per) L.piece = 2 * up(4 * N * H * (size_t)d.D * d.V) + up(4 * kda::MAX_PIECES) + up(4 * chd);
     return L;
 }
 
@@ -128,7 +135,7 @@ kda::Table carve_table(Carver& c, const Dims& d) {
 }
 
 void carve_fwd(Carver& c, const Dims& d, kda::Fwd& f, bool extra) {
-    const size_t chd = (size_t)d.NC * d.H, D = d.D, BT = kda::BT;
+    const size_t chd = (size_t)d.NC * d.H, D = d.WD, BT = kda::BT;
     f.W = c.take<float>(4 * chd * BT * D);
     f.U = c.take<float>(4 * chd * BT * D);
     f.KG = c.take<float>(4 * chd * BT * D);
@@ -146,7 +153,7 @@ void carve_fwd(Carver& c, const Dims& d, kda::Fwd& f, bool extra) {
 }
 
 void carve_bwd(Carver& c, const Dims& d, kda::Bwd& b) {
-    const size_t chd = (size_t)d.NC * d.H, D = d.D, BT = kda::BT;
+    const size_t chd = (size_t)d.NC * d.H, D = d.WD, BT = kda::BT;
     b.P = c.take<float>(4 * chd * BT * D);
     b.QS = c.take<float>(4 * chd * BT * D);
     b.PS = c.take<float>(4 * chd * BT * D);
@@ -159,7 +166,7 @@ void carve_bwd(Carver& c, const Dims& d, kda::Bwd& b) {
 }
 
 void carve_fwd_tc(Carver& c, const Dims& d, kda::FwdTC& f, bool bwd_arrays) {
-    const size_t chd = (size_t)d.NC * d.H, D = d.D, BT = kda::BT;
+    const size_t chd = (size_t)d.NC * d.H, D = d.WD, BT = kda::BT;
     std::memset(&f, 0, sizeof(f));
     f.W = c.take<__nv_bfloat16>(2 * chd * BT * D);
     f.KG = c.take<__nv_bfloat16>(2 * chd * BT * D);
@@ -177,7 +184,7 @@ void carve_fwd_tc(Carver& c, const Dims& d, kda::FwdTC& f, bool bwd_arrays) {
 }
 
 void carve_bwd_tc(Carver& c, const Dims& d, kda::BwdTC& b, kda::Bwd& scr) {
-    const size_t chd = (size_t)d.NC * d.H, D = d.D, BT = kda::BT;
+    const size_t chd = (size_t)d.NC * d.H, D = d.WD, BT = kda::BT;
     b.SBP = c.take<__nv_bfloat16>(2 * chd * D * D);
     b.P = c.take<__nv_bfloat16>(2 * chd * BT * D);
     std::memset(&scr, 0, sizeof(scr));
@@ -202,14 +209,20 @@ kda::Shape shape_of(const kda_problem* p, const Dims& d) {
     return s;
 }
 
-// Widths other than K = V = 128 or 256 (and, fp32 I/O, 64) run zero-padded to D (0: no
-// padding): bf16 I/O at K <= 128 goes to 128, the tensor-core width; fp32 I/O to 64 when both
-// widths fit, else 128; K > 128 to 256.
+// The width every key- and value-side tensor is zero-padded to (0: no padding). bf16 I/O with
+// K, V <= 128 runs on the tensor cores at their own widths when both are multiples of 8 (the
+// tensor maps read the missing columns as zeros) and the in-operator prologue, built for
+// K = 64, 128 and 256, is off or fits; otherwise bf16 pads to 128. fp32 I/O runs K = V = 64 or
+// 128 as they are and pads to 64 when both fit, else 128. K > 128 pads to 256 (K = V = 256 as is).
 int pad_width(const kda_problem* p) {
     const bool bf16 = p->io == KDA_BF16;
     if (p->K == p->V && (p->K == 128 || p->K == 256 || (p->K == 64 && !bf16))) return 0;
     if (p->K > 128) return 256;
-    if (bf16) return 128;
+    if (bf16) {
+        const bool prologue = p->A_log || p->qk_l2norm;
+        if (p->V <= 128 && p->K % 8 == 0 && p->V % 8 == 0 && (!prologue || p->K == 64 || p->K == 128)) return 0;
+        return 128;
+    }
     return (p->K <= 64 && p->V <= 64) ? 64 : 128;
 }
 // The padded buffers, in a fixed order after the inner problem's workspace (base NULL: size only).
@@ -421,7 +434,7 @@ kda_status cuda_fail(cudaError_t e, const char* where) {
     return fail(KDA_ERR_CUDA, std::string(where) + ": " + cudaGetErrorString(e));
 }
 
-size_t state_bytes(const Dims& d) { return sizeof(float) * (size_t)d.N * d.H * d.D * d.D; }
+size_t state_bytes(const Dims& d) { return sizeof(float) * (size_t)d.N * d.H * d.D * d.V; }
 
 // ------------------------------------------------------------------ tracing
 struct Prof {
@@ -974,8 +987,8 @@ static kda_status chunk_bwd_gva(const kda_problem* p, const void* dout, const fl
     return e == cudaSuccess ? KDA_OK : cuda_fail(e, "grouped heads: reduce dq, dk");
 }
 
-// Widths other than K = V = 64 or 128: every key- and value-side tensor zero-padded to the
-// working width after the inner problem's workspace, outputs and gradients cropped back.
+// Widths pad_width pads: every key- and value-side tensor zero-padded to the working width after
+// the inner problem's workspace, outputs and gradients cropped back.
 struct PadIo {
     const kda_problem* p;
     const Dims& d;

@@ -56,6 +56,8 @@ __device__ __forceinline__ void dstate_chunk(int c, int h, const Shape& s, const
     if (len <= 0) return;
     const int tok0 = t.chunk_tok0[c];
     const int H = s.H;
+    const int Vw = s.V;   // token rows of dO, v, write and of dv, dwrite (V = D but for the wide chunks
+                          // of the tensor-core path, whose rows may be narrower)
     const size_t ch = (size_t)c * H + h;
     const int lane = tid & 31, warp = tid >> 5;
 
@@ -66,7 +68,9 @@ __device__ __forceinline__ void dstate_chunk(int c, int h, const Shape& s, const
     auto load_block = [&](int v0) {
         auto e = [&](int r, int col) { return IMG ? tile_el(BT, r, v0 + col) : r * D + v0 + col; };
         tile_copy<BT, DC>(
-            [&](int r, int col) { return (r < len) ? ldg(dout + ((size_t)(tok0 + r) * H + h) * D + v0 + col) : 0.f; },
+            [&](int r, int col) {
+                return (r < len && v0 + col < Vw) ? ldg(dout + ((size_t)(tok0 + r) * H + h) * Vw + v0 + col) : 0.f;
+            },
             [&](int r, int col, float x) { sO[r * LD + col] = x; });
         tile_copy<BT, DC>([&](int r, int col) { return ldg(P + e(r, col)); },
                           [&](int r, int col, float x) { sP[r * LD + col] = x; });
@@ -99,13 +103,14 @@ __device__ __forceinline__ void dstate_chunk(int c, int h, const Shape& s, const
                     const float bt = wr ? 0.f : ld(beta + tok);
                     for (int cc = lane; cc < DC; cc += 32) {
                         const int col = v0 + cc;
-                        const float p = sP[r * LD + cc], vv = ld(v + tok * D + col);
+                        if (col >= Vw) break;
+                        const float p = sP[r * LD + cc], vv = ld(v + tok * Vw + col);
                         if (wr) {
-                            st(dv + tok * D + col, ld(wr + tok * D + col) * p);
-                            st(static_cast<TI*>(gd.dwrite) + tok * D + col, vv * p);
+                            st(dv + tok * Vw + col, ld(wr + tok * Vw + col) * p);
+                            st(static_cast<TI*>(gd.dwrite) + tok * Vw + col, vv * p);
                         } else {
                             dbw[i] = fmaf(vv, p, dbw[i]);
-                            st(dv + tok * D + col, bt * p);
+                            st(dv + tok * Vw + col, bt * p);
                         }
                     }
                 }
@@ -216,6 +221,8 @@ __device__ __forceinline__ void intra_chunk(int c, int h, const Shape& s, const 
     if (len <= 0) return;
     const int tok0 = t.chunk_tok0[c];
     const int H = s.H;
+    const int Kw = s.K;   // token rows of q, k, g, erase and of dq, dk, dg, derase (K = D but for the
+                          // wide chunks of the tensor-core path, whose rows may be narrower)
     const size_t ch = (size_t)c * H + h;
     const float scale = s.scale;
     const int lane = tid & 31, warp = tid >> 5;
@@ -232,7 +239,7 @@ __device__ __forceinline__ void intra_chunk(int c, int h, const Shape& s, const 
     // GatedDeltaNet-2: the erase vector takes beta's place on the key side (E = b .* K exp(G))
     const TI* er = static_cast<const TI*>(gd.erase);
     auto ebeta = [&](int r, int gcol) {
-        return er ? ((r < len) ? ld(er + ((size_t)(tok0 + r) * H + h) * D + gcol) : 0.f) : sBeta[r];
+        return er ? ((r < len && gcol < Kw) ? ld(er + ((size_t)(tok0 + r) * H + h) * Kw + gcol) : 0.f) : sBeta[r];
     };
     const float* QS = b.QS + ch * BT * D;
     const float* PS = b.PS + ch * BT * D;
@@ -246,15 +253,16 @@ __device__ __forceinline__ void intra_chunk(int c, int h, const Shape& s, const 
     for (int cb = 0; cb < NB; ++cb) {
         const int c0 = cb * DC;
         if (cb > 0) __syncthreads();   // the previous block's tiles are no longer read
-        auto off = [&](int r, int col) { return ((size_t)(tok0 + r) * H + h) * D + c0 + col; };
-        tile_copy<BT, DC>([&](int r, int col) { return r < len ? ldg(k + off(r, col)) : 0.f; },
+        auto off = [&](int r, int col) { return ((size_t)(tok0 + r) * H + h) * Kw + c0 + col; };
+        tile_copy<BT, DC>([&](int r, int col) { return (r < len && c0 + col < Kw) ? ldg(k + off(r, col)) : 0.f; },
                           [&](int r, int col, float x) { sK[r * LD + col] = x; });
-        tile_copy<BT, DC>([&](int r, int col) { return r < len ? ldg(q + off(r, col)) : 0.f; },
+        tile_copy<BT, DC>([&](int r, int col) { return (r < len && c0 + col < Kw) ? ldg(q + off(r, col)) : 0.f; },
                           [&](int r, int col, float x) { sQ[r * LD + col] = x; });
         tile_copy<BT, DC>(
             [&](int r, int col) {
                 if (GATE == 0 || r >= len) return 0.f;
-                return (GATE == 2 ? ldg(g + off(r, col)) : ldg(g + (size_t)(tok0 + r) * H + h)) * LOG2E;
+                if (GATE == 2) return c0 + col < Kw ? ldg(g + off(r, col)) * LOG2E : 0.f;
+                return ldg(g + (size_t)(tok0 + r) * H + h) * LOG2E;
             },
             [&](int r, int col, float x) { sG[r * LD + col] = x; });
         __syncthreads();
@@ -460,8 +468,8 @@ __device__ __forceinline__ void intra_chunk(int c, int h, const Shape& s, const 
                 const float Et = aE[ii][jj] + gam * PS[o];                    // gamma * E_bar
                 const float Yt = aY[ii][jj] + FB[o] * exp2f(gl2[col] - gm);   // Y_bar / gamma
                 const float kv = sK[m * LD + col], qv = sQ[m * LD + col], bt = ebeta(m, c0 + col);
-                if (m < len) {
-                    const size_t go = ((size_t)(tok0 + m) * H + h) * D + c0 + col;
+                if (m < len && c0 + col < Kw) {
+                    const size_t go = ((size_t)(tok0 + m) * H + h) * Kw + c0 + col;
                     st(dq + go, scale * Qt);
                     st(dk + go, bt * Et + Yt);
                     if (er) st(static_cast<TI*>(gd.derase) + go, kv * Et);   // db = K exp(G) .* E_bar
@@ -486,7 +494,7 @@ __device__ __forceinline__ void intra_chunk(int c, int h, const Shape& s, const 
                 float acc = 0.f;
                 for (int r = len - 1; r >= 0; --r) {
                     acc += sF4[r * LD + tid];
-                    dg[((size_t)(tok0 + r) * H + h) * D + c0 + tid] = acc;
+                    if (c0 + tid < Kw) dg[((size_t)(tok0 + r) * H + h) * Kw + c0 + tid] = acc;
                 }
             }
         } else {

@@ -29,11 +29,14 @@ __host__ __device__ __forceinline__ int tile_el(int R, int r, int col) {
 }
 
 // TMA tensor maps of a token-major input [Ttot][H][D] whose boxes are one
-// head's 64-token chunk rows: bf16 in two 64-column boxes with the 128-byte
-// swizzle (each lands as one atom column of a K-major operand tile), fp32 in
-// one unswizzled [64][D] box. False if the map cannot be encoded.
+// head's 64-token chunk rows: bf16 in 64-column boxes with the 128-byte swizzle
+// (each lands as one atom column of a K-major operand tile), fp32 in one
+// unswizzled [64][box_x] box (box_x = D when 0). D may be narrower than the
+// 128-column tiles (a multiple of 8 for bf16, 4 for fp32): the columns past D
+// read as zeros and stores past D are dropped. False if the map cannot be
+// encoded.
 bool tmap_rows_bf16(CUtensorMap* m, const void* base, int Ttot, int H, int D);
-bool tmap_rows_f32(CUtensorMap* m, const void* base, int Ttot, int H, int D);
+bool tmap_rows_f32(CUtensorMap* m, const void* base, int Ttot, int H, int D, int box_x = 0);
 
 // Chunk bookkeeping built on the device from cu_seqlens (or from B, T).
 struct Table {

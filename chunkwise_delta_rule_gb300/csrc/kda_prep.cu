@@ -52,24 +52,29 @@ __device__ __forceinline__ void prep_chunk(int c, int h, const Shape& s, const T
     const size_t ch = (size_t)c * H + h;
 
     if (tid < BT) sBeta[tid] = (tid < n && !gd.erase) ? ldg(beta + (size_t)(tok0 + tid) * H + h) : 0.f;
-    // GatedDeltaNet-2: the erase vector takes beta's place on the key rows of E
+    // GatedDeltaNet-2: the erase vector takes beta's place on the key rows of E. The token rows of
+    // q, k, g and erase are K wide, those of v and write V wide (K = V = D but for the wide chunks
+    // of the tensor-core path, whose inputs may be narrower than its 128 columns); columns past
+    // them read as zeros.
+    const int Kw = s.K, Vw = s.V;
     const TI* er = static_cast<const TI*>(gd.erase);
     auto ebeta = [&](int r, int gcol) {
-        return er ? ((r < n) ? ld(er + ((size_t)(tok0 + r) * H + h) * D + gcol) : 0.f) : sBeta[r];
+        return er ? ((r < n && gcol < Kw) ? ld(er + ((size_t)(tok0 + r) * H + h) * Kw + gcol) : 0.f) : sBeta[r];
     };
     // ---- chunk rows of features c0 .. c0+DC-1 (rows >= n are zero keys/queries
     // and zero decay), then a1: inclusive cumsum down each feature column
     // (padding rows keep G[n-1])
     auto load_block = [&](int c0) {
-        auto off = [&](int r, int col) { return ((size_t)(tok0 + r) * H + h) * D + c0 + col; };
-        tile_copy<BT, DC>([&](int r, int col) { return r < n ? ldg(k + off(r, col)) : 0.f; },
+        auto off = [&](int r, int col) { return ((size_t)(tok0 + r) * H + h) * Kw + c0 + col; };
+        tile_copy<BT, DC>([&](int r, int col) { return (r < n && c0 + col < Kw) ? ldg(k + off(r, col)) : 0.f; },
                           [&](int r, int col, float x) { sK[r * LD + col] = x; });
-        tile_copy<BT, DC>([&](int r, int col) { return r < n ? ldg(q + off(r, col)) : 0.f; },
+        tile_copy<BT, DC>([&](int r, int col) { return (r < n && c0 + col < Kw) ? ldg(q + off(r, col)) : 0.f; },
                           [&](int r, int col, float x) { sQ[r * LD + col] = x; });
         tile_copy<BT, DC>(
             [&](int r, int col) {
                 if (GATE == 0 || r >= n) return 0.f;
-                return (GATE == 2 ? ldg(g + off(r, col)) : ldg(g + (size_t)(tok0 + r) * H + h)) * LOG2E;
+                if (GATE == 2) return c0 + col < Kw ? ldg(g + off(r, col)) * LOG2E : 0.f;
+                return ldg(g + (size_t)(tok0 + r) * H + h) * LOG2E;
             },
             [&](int r, int col, float x) { sG[r * LD + col] = x; });
         __syncthreads();
@@ -201,8 +206,8 @@ __device__ __forceinline__ void prep_chunk(int c, int h, const Shape& s, const T
         __syncthreads();  // all reads of sQ (queries) are done
         tile_copy<BT, DC>(
             [&](int r, int col) {
-                if (r >= n) return 0.f;
-                const size_t off = ((size_t)(tok0 + r) * H + h) * D + c0 + col;
+                if (r >= n || c0 + col >= Vw) return 0.f;
+                const size_t off = ((size_t)(tok0 + r) * H + h) * Vw + c0 + col;
                 const float wv = gd.write ? ldg(static_cast<const TI*>(gd.write) + off) : sBeta[r];
                 return wv * ldg(v + off);
             },

@@ -94,6 +94,8 @@ __device__ __forceinline__ void bscan_fill(uint32_t stg, const FwdTC& f, size_t 
 // Compute warps: per chunk (last to first) S+bar^T -> bf16 A operand, then
 // (while R_bar runs) S_bar^T <- S+bar^T diag(lambda); R_bar^T -> bf16 A operands;
 // then, while the state adjoint update runs, S+bar and the previous P to HBM.
+// NARROW: the states are [K][V] with K, V below D; otherwise [D][D], folded into the addressing.
+template <bool NARROW>
 __device__ __forceinline__ void bscan_compute(const Shape& s, const float* __restrict__ dht, const Table& t,
                                               const FwdTC& f, const BwdTC& b, float* __restrict__ dh0,
                                               unsigned char* base, uint64_t* bar, uint32_t tb, int nseq, int h,
@@ -106,13 +108,15 @@ __device__ __forceinline__ void bscan_compute(const Shape& s, const float* __res
     const int vcol = 32 * quad + lane;
     const int kb = 64 * half, ib = 32 * half;
     const uint32_t tl = tc::taddr(tb, 32 * quad, 0);
-    const size_t st_off = ((size_t)nseq * H + h) * D * D;
+    const int K = NARROW ? s.K : D, V = NARROW ? s.V : D;   // the state's widths ([K][V] per sequence and head)
+    const size_t st_off = ((size_t)nseq * H + h) * K * V;
 
 #pragma unroll 1
     for (int cb = kb; cb < kb + 64; cb += 16) {
         float a[16];
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj) a[jj] = dht ? dht[st_off + (size_t)(cb + jj) * D + vcol] : 0.f;
+        for (int jj = 0; jj < 16; ++jj)
+            a[jj] = (dht && cb + jj < K && vcol < V) ? dht[st_off + (size_t)(cb + jj) * V + vcol] : 0.f;
         tc::tmem_st16(tl + cb, a);
     }
     tc::tmem_wait_st();
@@ -245,7 +249,8 @@ __device__ __forceinline__ void bscan_compute(const Shape& s, const float* __res
             tc::tmem_ld16(tl + cb, a);
             tc::tmem_wait_ld();
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) dh0[st_off + (size_t)(cb + jj) * D + vcol] = a[jj];
+            for (int jj = 0; jj < 16; ++jj)
+                if (cb + jj < K && vcol < V) dh0[st_off + (size_t)(cb + jj) * V + vcol] = a[jj];
         }
     }
 }
@@ -329,6 +334,7 @@ __device__ __forceinline__ void bscan_issue(const Shape& s, const Table& t, cons
 // threads: warps 0..7 compute, warp 8 issues, further warps only meet the CTA barriers. tb: 512 TMEM
 // columns allocated by the caller. flags (the joint schedule): a ready flag per (chunk slot, head), set
 // once the chunk's S+bar and P are in HBM.
+template <bool NARROW>
 __device__ __forceinline__ void bscan_body(const Shape& s, const CUtensorMap* tmo, const float* __restrict__ dht,
                                            const Table& t, const FwdTC& f, const BwdTC& b, float* __restrict__ dh0,
                                            int nseq, int h, int plo, int pl, int* flags, unsigned char* base,
@@ -355,7 +361,7 @@ __device__ __forceinline__ void bscan_body(const Shape& s, const CUtensorMap* tm
     if (issuer)
         bscan_issue(s, t, f, b, tmo, sb, bar, full, tb, h, c0, c1, filled, waited, flags);
     else if (warp < ST / 32)
-        bscan_compute(s, dht, t, f, b, dh0, base, bar, tb, nseq, h, c0, c1, flags);
+        bscan_compute<NARROW>(s, dht, t, f, b, dh0, base, bar, tb, nseq, h, c0, c1, flags);
     // a bulk fill still in flight (only after a timeout) lands before the CTA moves on
     if (issuer && (tid & 31) == 0)
         for (; waited < filled; ++waited) tc::mbar_wait(&full[waited & 1], (waited >> 1) & 1);
@@ -390,7 +396,7 @@ __global__ void __launch_bounds__(ST_ALL, 1)
     const uint32_t tb = *tslot;
     // sequences in the table's order (longest first), every head of one before the next
     const int lin = (int)(blockIdx.x + blockIdx.y * gridDim.x);
-    bscan_body(s, &tmo, dht, t, f, b, dh0, t.seq_order[lin / s.H], lin % s.H, plo, pl, nullptr, base, tb);
+    bscan_body<true>(s, &tmo, dht, t, f, b, dh0, t.seq_order[lin / s.H], lin % s.H, plo, pl, nullptr, base, tb);
     tc::fence_before_sync();
     __syncthreads();
     if (threadIdx.x < 32) tc::tmem_dealloc(tb, 512);
@@ -574,7 +580,9 @@ __device__ __forceinline__ bool cons_wait(uint64_t* b, int& w, int32_t* err) {
 // The consumer loop of one CTA (CT threads): units from the launch's index space until none is left.
 // tb: 512 TMEM columns allocated by the caller. In the joint schedule the X tiles of a unit are loaded
 // once its ready flag is set.
-template <int GATE, bool GD2>
+// NARROW: the token rows of the inputs and gradients are K and V wide (multiples of 8, at most D);
+// otherwise both are D, which the compiler folds into the addressing.
+template <int GATE, bool GD2, bool NARROW>
 __device__ __forceinline__ void cons_body(const Shape& s, const CUtensorMap* tmq_, const CUtensorMap* tmk_,
                                           const CUtensorMap* tmo_, const CUtensorMap* tmg_, const CUtensorMap* tmv_,
                                           const bf16* __restrict__ beta, const float* __restrict__ g, const Table& t,
@@ -583,6 +591,7 @@ __device__ __forceinline__ void cons_body(const Shape& s, const CUtensorMap* tmq
                                           float* __restrict__ dg, const Gdn2& gd, const ConsPiece& pc,
                                           unsigned char* base, uint32_t tb) {
     const CUtensorMap &tmq = *tmq_, &tmk = *tmk_, &tmo = *tmo_, &tmg = *tmg_, &tmv = *tmv_;
+    const int Kw = NARROW ? s.K : D, Vw = NARROW ? s.V : D;   // row widths of the key- and value-side tensors
     float* sA = reinterpret_cast<float*>(base + C_A);
     const unsigned char* sK = base + C_K;
     const unsigned char* sQ = base + C_Q;
@@ -746,8 +755,8 @@ __device__ __forceinline__ void cons_body(const Shape& s, const CUtensorMap* tmq
         for (int uu = 0; uu < BT * 16 / CT; ++uu) {   // 16 threads per row, 8 values each
             const int idx = tid + CT * uu, r = idx >> 4, cc = idx & 15;
             float acc = 0.f;
-            if (r < n) {
-                const size_t tok = (size_t)(tok0 + r) * H + h;
+            if (r < n && cc * 8 < Vw) {
+                const size_t tok = (size_t)(tok0 + r) * H + h;   // value rows of width V
                 const float bt = sBeta[r];
                 const uint4 pp = *reinterpret_cast<const uint4*>(base + X_OP + tc::sw128_off(2 * BT, BT + r, cc * 16));
                 const uint4 vv = *reinterpret_cast<const uint4*>(base + X_V + tc::sw128_off(BT, r, cc * 16));
@@ -755,7 +764,7 @@ __device__ __forceinline__ void cons_body(const Shape& s, const CUtensorMap* tmq
                 const bf16* vv2 = reinterpret_cast<const bf16*>(&vv);
                 uint32_t out[4], wout[4];
                 if (GD2) {   // GatedDeltaNet-2: dv = w .* P, dw = v .* P
-                    const uint4 ww = *reinterpret_cast<const uint4*>(static_cast<const bf16*>(gd.write) + tok * D + cc * 8);
+                    const uint4 ww = *reinterpret_cast<const uint4*>(static_cast<const bf16*>(gd.write) + tok * Vw + cc * 8);
                     const bf16* ww2 = reinterpret_cast<const bf16*>(&ww);
 #pragma unroll
                     for (int e = 0; e < 8; e += 2) {
@@ -763,7 +772,7 @@ __device__ __forceinline__ void cons_body(const Shape& s, const CUtensorMap* tmq
                         out[e / 2] = tc::pack_bf16(__bfloat162float(ww2[e]) * p0, __bfloat162float(ww2[e + 1]) * p1);
                         wout[e / 2] = tc::pack_bf16(__bfloat162float(vv2[e]) * p0, __bfloat162float(vv2[e + 1]) * p1);
                     }
-                    *reinterpret_cast<uint4*>(static_cast<bf16*>(gd.dwrite) + tok * D + cc * 8) =
+                    *reinterpret_cast<uint4*>(static_cast<bf16*>(gd.dwrite) + tok * Vw + cc * 8) =
                         make_uint4(wout[0], wout[1], wout[2], wout[3]);
                 } else {
 #pragma unroll
@@ -774,7 +783,7 @@ __device__ __forceinline__ void cons_body(const Shape& s, const CUtensorMap* tmq
                         out[e / 2] = tc::pack_bf16(bt * p0, bt * p1);
                     }
                 }
-                *reinterpret_cast<uint4*>(dv + tok * D + cc * 8) = make_uint4(out[0], out[1], out[2], out[3]);
+                *reinterpret_cast<uint4*>(dv + tok * Vw + cc * 8) = make_uint4(out[0], out[1], out[2], out[3]);
             }
 #pragma unroll
             for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o, 16);
@@ -789,8 +798,9 @@ __device__ __forceinline__ void cons_body(const Shape& s, const CUtensorMap* tmq
             if (tid < BT)
                 beta_nx = (tid < nm[1] && !GD2) ? beta[(size_t)(nm[2] + tid) * H + nh] : __float2bfloat16_rn(0.f);
             if (GD2 && (tid >> 2) < nm[1]) {
+                const int w = (tid & 2) ? Vw : Kw;   // the row widths of the write and erase vectors
                 const bf16* vec = static_cast<const bf16*>((tid & 2) ? gd.write : gd.erase);
-                tc::prefetch_l2(vec + ((size_t)(nm[2] + (tid >> 2)) * H + nh) * D + (tid & 1) * 64);
+                if ((tid & 1) * 64 < w) tc::prefetch_l2(vec + ((size_t)(nm[2] + (tid >> 2)) * H + nh) * w + (tid & 1) * 64);
             }
         }
         // cumsum (4 segments of 16 rows per feature: thread = key kr, rows jb .. jb+15, the same
@@ -913,8 +923,8 @@ __device__ __forceinline__ void cons_body(const Shape& s, const CUtensorMap* tmq
                     const float qv = bf_lo_hi(qw[q16 >> 1], q16 & 1);
                     const float av = (GATE == 2) ? al[q16] : 1.f;
                     const bool in = j < n;
-                    const float eb = GD2 ? (in ? bfx(static_cast<const bf16*>(gd.erase) +
-                                                     ((size_t)(tok0 + j) * H + h) * D + kr) : 0.f)
+                    const float eb = GD2 ? ((in && kr < Kw) ? bfx(static_cast<const bf16*>(gd.erase) +
+                                                                   ((size_t)(tok0 + j) * H + h) * Kw + kr) : 0.f)
                                          : bq[e];
                     ea[e] = in ? eb * kv * av : 0.f;
                     qa[e] = in ? scale * qv * av : 0.f;
@@ -999,8 +1009,9 @@ __device__ __forceinline__ void cons_body(const Shape& s, const CUtensorMap* tmq
                                                   __fmul2_rn(__fmul2_rn(al2, nc22), make_float2(tps[e], tps[e + 1])));
                     float2 be2;
                     if (GD2) {
-                        const bf16* er = static_cast<const bf16*>(gd.erase) + ((size_t)(tok0 + j) * H + h) * D + kr;
-                        be2 = make_float2((j < n) ? bfx(er) : 0.f, (j + 1 < n) ? bfx(er + (size_t)H * D) : 0.f);
+                        const bf16* er = static_cast<const bf16*>(gd.erase) + ((size_t)(tok0 + j) * H + h) * Kw + kr;
+                        const bool kin = kr < Kw;   // erase rows of width K
+                        be2 = make_float2((kin && j < n) ? bfx(er) : 0.f, (kin && j + 1 < n) ? bfx(er + (size_t)H * Kw) : 0.f);
                     } else {
                         be2 = make_float2(bv[e], bv[e + 1]);
                     }
@@ -1019,10 +1030,13 @@ __device__ __forceinline__ void cons_body(const Shape& s, const CUtensorMap* tmq
                     als[e] = al2.x;
                     als[e + 1] = al2.y;
                 }
-                const size_t row0 = ((size_t)(tok0 + j0) * H + h) * D + 32 * quad;
-                tc::warp_store_t8(stg, dqv, dq + row0, (size_t)H * D, nrow, lane);
+                // key rows of width K: this warp's 32 keys from 32 quad, wk of them present
+                const size_t row0 = ((size_t)(tok0 + j0) * H + h) * Kw + 32 * quad;
+                const int wk = Kw - 32 * quad;
+                if (wk > 0) tc::warp_store_t8(stg, dqv, dq + row0, (size_t)H * Kw, nrow, lane, wk);
                 if (GD2) {
-                    tc::warp_store_t8(stg, dbp, static_cast<bf16*>(gd.derase) + row0, (size_t)H * D, nrow, lane);
+                    if (wk > 0)
+                        tc::warp_store_t8(stg, dbp, static_cast<bf16*>(gd.derase) + row0, (size_t)H * Kw, nrow, lane, wk);
                 } else {
                     const float tot = tc::warp_sum8_spread(dbp, lane);
                     if ((lane & 3) == 0) sRowP[quad * BT + j0 + (lane >> 2)] = tot;
@@ -1055,7 +1069,9 @@ __device__ __forceinline__ void cons_body(const Shape& s, const CUtensorMap* tmq
                 }
                 endp += ep2.x + ep2.y;
             }
-            tc::warp_store_t8(stg, dkv, dk + ((size_t)(tok0 + j0) * H + h) * D + 32 * quad, (size_t)H * D, nrow, lane);
+            if (Kw > 32 * quad)
+                tc::warp_store_t8(stg, dkv, dk + ((size_t)(tok0 + j0) * H + h) * Kw + 32 * quad, (size_t)H * Kw, nrow,
+                                  lane, Kw - 32 * quad);
             if (GATE == 2) {
 #pragma unroll
                 for (int e = 7; e >= 0; --e) {
@@ -1095,7 +1111,7 @@ __device__ __forceinline__ void cons_body(const Shape& s, const CUtensorMap* tmq
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
                 const int j = jb + e;
-                if (j < n) dg[((size_t)(tok0 + j) * H + h) * D + kr] = gx[e] + off;
+                if (j < n && kr < Kw) dg[((size_t)(tok0 + j) * H + h) * Kw + kr] = gx[e] + off;
             }
         } else if (GATE == 1) {
             // scalar gate: dg_j = sum over j' >= j of the feature sums of G_bar, plus the endpoint
@@ -1125,7 +1141,7 @@ __device__ __forceinline__ void cons_body(const Shape& s, const CUtensorMap* tmq
     }
 }
 
-template <int GATE, bool GD2>
+template <int GATE, bool GD2, bool NARROW>
 __global__ void __launch_bounds__(CT, 1)
     k_bwd_consumer_tc(Shape s, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmo, const __grid_constant__ CUtensorMap tmg,
@@ -1145,7 +1161,7 @@ __global__ void __launch_bounds__(CT, 1)
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tb = *tslot;
-    cons_body<GATE, GD2>(s, &tmq, &tmk, &tmo, &tmg, &tmv, beta, g, t, f, bw, dq, dk, dv, dbeta, dg, gd, pc, base, tb);
+    cons_body<GATE, GD2, NARROW>(s, &tmq, &tmk, &tmo, &tmg, &tmv, beta, g, t, f, bw, dq, dk, dv, dbeta, dg, gd, pc, base, tb);
     tc::fence_before_sync();
     __syncthreads();
     if (threadIdx.x < 32) tc::tmem_dealloc(tb, 512);
@@ -1156,7 +1172,7 @@ __global__ void __launch_bounds__(CT, 1)
 // the other CTAs in the consumer loop, which takes the units latest chunk first and waits for each
 // unit's flag before loading its scan outputs. No CTA waits for one that is not running: the launch
 // is cooperative, so all of them are resident, and the scans never wait for the consumers.
-template <int GATE, bool GD2>
+template <int GATE, bool GD2, bool NARROW>
 __global__ void __launch_bounds__(CT, 1)
     k_bwd_joint_tc(Shape s, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmo, const __grid_constant__ CUtensorMap tmg,
@@ -1177,51 +1193,53 @@ __global__ void __launch_bounds__(CT, 1)
     tc::fence_after_sync();
     const uint32_t tb = *tslot;
     if ((int)blockIdx.x < s.N * s.H) {
-        bscan_body(s, &tmo, dht, t, f, bw, dh0, t.seq_order[(int)blockIdx.x / s.H], (int)blockIdx.x % s.H, 0, 0,
+        bscan_body<NARROW>(s, &tmo, dht, t, f, bw, dh0, t.seq_order[(int)blockIdx.x / s.H], (int)blockIdx.x % s.H, 0, 0,
                    pc.flags, base, tb);
         tc::fence_async_smem();   // the scan's shared-memory writes before the consumer's tile loads land
         tc::fence_before_sync();
         __syncthreads();
         tc::fence_after_sync();
     }
-    cons_body<GATE, GD2>(s, &tmq, &tmk, &tmo, &tmg, &tmv, beta, g, t, f, bw, dq, dk, dv, dbeta, dg, gd, pc, base, tb);
+    cons_body<GATE, GD2, NARROW>(s, &tmq, &tmk, &tmo, &tmg, &tmv, beta, g, t, f, bw, dq, dk, dv, dbeta, dg, gd, pc, base, tb);
     tc::fence_before_sync();
     __syncthreads();
     if (threadIdx.x < 32) tc::tmem_dealloc(tb, 512);
 }
 
-template <int GATE, bool GD2>
+template <int GATE, bool GD2, bool NARROW>
 cudaError_t run_consumer(const Shape& s, const void* q, const void* k, const void* v, const void* beta,
                          const float* g, const void* dout, Table t, FwdTC f, BwdTC b, void* dq, void* dk,
                          void* dv, void* dbeta, float* dg, cudaStream_t st, const Gdn2& gd, const ConsPiece& pc) {
-    cudaError_t e = set_smem_once<k_bwd_consumer_tc<GATE, GD2>>(CONS_SMEM);
+    cudaError_t e = set_smem_once<k_bwd_consumer_tc<GATE, GD2, NARROW>>(CONS_SMEM);
     if (e != cudaSuccess) return e;
     CUtensorMap mq, mk, mo, mg, mv;
     memset(&mg, 0, sizeof(mg));
-    if (!tmap_rows_bf16(&mq, q, s.Ttot, s.H, D) || !tmap_rows_bf16(&mk, k, s.Ttot, s.H, D) ||
-        !tmap_rows_bf16(&mo, dout, s.Ttot, s.H, D) || !tmap_rows_bf16(&mv, v, s.Ttot, s.H, D) ||
-        (GATE == 2 && !tmap_rows_f32(&mg, g, s.Ttot, s.H, D)))
+    // the inputs at their own widths K, V (<= D): the boxes' columns past them read as zeros
+    if (!tmap_rows_bf16(&mq, q, s.Ttot, s.H, s.K) || !tmap_rows_bf16(&mk, k, s.Ttot, s.H, s.K) ||
+        !tmap_rows_bf16(&mo, dout, s.Ttot, s.H, s.V) || !tmap_rows_bf16(&mv, v, s.Ttot, s.H, s.V) ||
+        (GATE == 2 && !tmap_rows_f32(&mg, g, s.Ttot, s.H, s.K, D)))
         return cudaErrorInvalidValue;
     const long units = pc.L ? (long)s.N * pc.L * s.H : (long)s.NC * s.H;
     if (units <= 0) return cudaSuccess;
     if (units > 0x7fffffffL) return cudaErrorInvalidValue;
     const int grid = (int)(units < sm_count() ? units : sm_count());   // one CTA per SM, persistent
-    k_bwd_consumer_tc<GATE, GD2><<<grid, CT, CONS_SMEM, st>>>(s, mq, mk, mo, mg, mv, (const bf16*)beta, g, t, f, b,
+    k_bwd_consumer_tc<GATE, GD2, NARROW><<<grid, CT, CONS_SMEM, st>>>(s, mq, mk, mo, mg, mv, (const bf16*)beta, g, t, f, b,
                                                          (bf16*)dq, (bf16*)dk, (bf16*)dv, (bf16*)dbeta, dg, gd, pc);
     return cudaGetLastError();
 }
 
-template <int GATE, bool GD2>
+template <int GATE, bool GD2, bool NARROW>
 cudaError_t run_joint(const Shape& s, const void* q, const void* k, const void* v, const void* beta, const float* g,
                       const void* dout, const float* dht, float* dh0, Table t, FwdTC f, BwdTC b, void* dq, void* dk,
                       void* dv, void* dbeta, float* dg, cudaStream_t st, const Gdn2& gd, const ConsPiece& pc) {
-    cudaError_t e = set_smem_once<k_bwd_joint_tc<GATE, GD2>>(JOINT_SMEM);
+    cudaError_t e = set_smem_once<k_bwd_joint_tc<GATE, GD2, NARROW>>(JOINT_SMEM);
     if (e != cudaSuccess) return e;
     CUtensorMap mq, mk, mo, mg, mv;
     memset(&mg, 0, sizeof(mg));
-    if (!tmap_rows_bf16(&mq, q, s.Ttot, s.H, D) || !tmap_rows_bf16(&mk, k, s.Ttot, s.H, D) ||
-        !tmap_rows_bf16(&mo, dout, s.Ttot, s.H, D) || !tmap_rows_bf16(&mv, v, s.Ttot, s.H, D) ||
-        (GATE == 2 && !tmap_rows_f32(&mg, g, s.Ttot, s.H, D)))
+    // the inputs at their own widths K, V (<= D): the boxes' columns past them read as zeros
+    if (!tmap_rows_bf16(&mq, q, s.Ttot, s.H, s.K) || !tmap_rows_bf16(&mk, k, s.Ttot, s.H, s.K) ||
+        !tmap_rows_bf16(&mo, dout, s.Ttot, s.H, s.V) || !tmap_rows_bf16(&mv, v, s.Ttot, s.H, s.V) ||
+        (GATE == 2 && !tmap_rows_f32(&mg, g, s.Ttot, s.H, s.K, D)))
         return cudaErrorInvalidValue;
     const int grid = sm_count();
     if (s.N * s.H > grid || !pc.flags || !pc.ctr) return cudaErrorInvalidValue;
@@ -1235,7 +1253,7 @@ cudaError_t run_joint(const Shape& s, const void* q, const void* k, const void* 
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_bwd_joint_tc<GATE, GD2>, s, mq, mk, mo, mg, mv, dht, dh0, (const bf16*)beta, g,
+    return cudaLaunchKernelEx(&cfg, k_bwd_joint_tc<GATE, GD2, NARROW>, s, mq, mk, mo, mg, mv, dht, dh0, (const bf16*)beta, g,
                               t, f, b, (bf16*)dq, (bf16*)dk, (bf16*)dv, (bf16*)dbeta, dg, gd, pc);
 }
 
@@ -1245,7 +1263,10 @@ cudaError_t launch_bwd_joint_tc(const Shape& s, int gate, const void* q, const v
                                 const void* beta, const float* g, const void* dout, const float* dht, float* dh0,
                                 Table t, FwdTC f, BwdTC b, void* dq, void* dk, void* dv, void* dbeta, float* dg,
                                 cudaStream_t st, const Gdn2& gd, const ConsPiece& pc) {
-#define KDA_JOINT(G, X) run_joint<G, X>(s, q, k, v, beta, g, dout, dht, dh0, t, f, b, dq, dk, dv, dbeta, dg, st, gd, pc)
+    const bool narrow = s.K != D || s.V != D;   // inputs narrower than the tiles
+#define KDA_JOINT(G, X)                                                                                          \
+    (narrow ? run_joint<G, X, true>(s, q, k, v, beta, g, dout, dht, dh0, t, f, b, dq, dk, dv, dbeta, dg, st, gd, pc) \
+            : run_joint<G, X, false>(s, q, k, v, beta, g, dout, dht, dh0, t, f, b, dq, dk, dv, dbeta, dg, st, gd, pc))
     switch (gate) {
         case 0: return gd.erase ? KDA_JOINT(0, true) : KDA_JOINT(0, false);
         case 1: return gd.erase ? KDA_JOINT(1, true) : KDA_JOINT(1, false);
@@ -1259,7 +1280,7 @@ cudaError_t launch_bwd_scan_tc(const Shape& s, const void* dout, const float* dh
     cudaError_t e = set_smem_once<k_bwd_scan_tc>(BSCAN_SMEM);
     if (e != cudaSuccess) return e;
     CUtensorMap mo;
-    if (!tmap_rows_bf16(&mo, dout, s.Ttot, s.H, D)) return cudaErrorInvalidValue;
+    if (!tmap_rows_bf16(&mo, dout, s.Ttot, s.H, s.V)) return cudaErrorInvalidValue;
     dim3 grid(s.N, s.H);
     k_bwd_scan_tc<<<grid, ST_ALL, BSCAN_SMEM, st>>>(s, mo, dht, t, f, b, dh0, pc.lo, pc.L);
     return cudaGetLastError();
@@ -1269,14 +1290,16 @@ cudaError_t launch_bwd_consumer_tc(const Shape& s, int gate, const void* q, cons
                                    const void* beta, const float* g, const void* dout, Table t, FwdTC f,
                                    BwdTC b, void* dq, void* dk, void* dv, void* dbeta, float* dg,
                                    cudaStream_t st, const Gdn2& gd, const ConsPiece& pc) {
+    const bool narrow = s.K != D || s.V != D;   // inputs narrower than the tiles
+#define KDA_CONS(G, X)                                                                                         \
+    (narrow ? run_consumer<G, X, true>(s, q, k, v, beta, g, dout, t, f, b, dq, dk, dv, dbeta, dg, st, gd, pc) \
+            : run_consumer<G, X, false>(s, q, k, v, beta, g, dout, t, f, b, dq, dk, dv, dbeta, dg, st, gd, pc))
     switch (gate) {
-        case 0: return gd.erase ? run_consumer<0, true>(s, q, k, v, beta, g, dout, t, f, b, dq, dk, dv, dbeta, dg, st, gd, pc)
-                                : run_consumer<0, false>(s, q, k, v, beta, g, dout, t, f, b, dq, dk, dv, dbeta, dg, st, gd, pc);
-        case 1: return gd.erase ? run_consumer<1, true>(s, q, k, v, beta, g, dout, t, f, b, dq, dk, dv, dbeta, dg, st, gd, pc)
-                                : run_consumer<1, false>(s, q, k, v, beta, g, dout, t, f, b, dq, dk, dv, dbeta, dg, st, gd, pc);
-        default: return gd.erase ? run_consumer<2, true>(s, q, k, v, beta, g, dout, t, f, b, dq, dk, dv, dbeta, dg, st, gd, pc)
-                                 : run_consumer<2, false>(s, q, k, v, beta, g, dout, t, f, b, dq, dk, dv, dbeta, dg, st, gd, pc);
+        case 0: return gd.erase ? KDA_CONS(0, true) : KDA_CONS(0, false);
+        case 1: return gd.erase ? KDA_CONS(1, true) : KDA_CONS(1, false);
+        default: return gd.erase ? KDA_CONS(2, true) : KDA_CONS(2, false);
     }
+#undef KDA_CONS
 }
 
 }  // namespace kda

@@ -217,8 +217,9 @@ __global__ void __launch_bounds__(PT, 2)
     // GatedDeltaNet-2: this chunk's erase and write rows (two 128-byte lines each) into L2 while
     // the cumsum runs; the operand pass reads them
     if (GD2 && (tid >> 2) < n) {
+        const int w = (tid & 2) ? s.V : s.K;   // the row widths of the write and erase vectors
         const bf16* vec = static_cast<const bf16*>((tid & 2) ? gd.write : gd.erase);
-        tc::prefetch_l2(vec + ((size_t)(tok0 + (tid >> 2)) * H + h) * D + (tid & 1) * 64);
+        if ((tid & 1) * 64 < w) tc::prefetch_l2(vec + ((size_t)(tok0 + (tid >> 2)) * H + h) * w + (tid & 1) * 64);
     }
     if (GATE != 2) {
         // scalar gate: the G tile repeats the token's log-decay; no gate: zeros
@@ -311,9 +312,9 @@ __global__ void __launch_bounds__(PT, 2)
                 const int i = (tid + PT * u) >> 4;
                 er_all[u] = wr_all[u] = make_uint4(0, 0, 0, 0);
                 if (i < n) {
-                    const size_t o = ((size_t)(tok0 + i) * H + h) * D + c8;
-                    er_all[u] = *reinterpret_cast<const uint4*>(static_cast<const bf16*>(gd.erase) + o);
-                    wr_all[u] = *reinterpret_cast<const uint4*>(static_cast<const bf16*>(gd.write) + o);
+                    const size_t row = (size_t)(tok0 + i) * H + h;   // widths K and V, zero past them
+                    if (c8 < s.K) er_all[u] = *reinterpret_cast<const uint4*>(static_cast<const bf16*>(gd.erase) + row * s.K + c8);
+                    if (c8 < s.V) wr_all[u] = *reinterpret_cast<const uint4*>(static_cast<const bf16*>(gd.write) + row * s.V + c8);
                 }
             }
         }
@@ -563,18 +564,21 @@ __device__ __forceinline__ void fscan_fill(uint32_t stg, const FwdTC& f, size_t 
 
 // The output of a full chunk from its staging tile (a [64][128] tile image) to
 // HBM: two TMA box stores, one per 64-column atom block (lane 0 of the caller).
-__device__ __forceinline__ void fscan_tma_out(const CUtensorMap* tmo, uint32_t ost, int tok0, int h, int lane) {
+// A box that would start past the value width V is not issued (its columns would all be dropped).
+__device__ __forceinline__ void fscan_tma_out(const CUtensorMap* tmo, uint32_t ost, int tok0, int h, int V, int lane) {
     if (lane == 0) {
         tc::tma_store3(tmo, 0, h, tok0, ost);
-        tc::tma_store3(tmo, 64, h, tok0, ost + BT * 128);
+        if (V > 64) tc::tma_store3(tmo, 64, h, tok0, ost + BT * 128);
         tc::bulk_commit();
     }
 }
 
 // Output rows [ib, ib+32) of a chunk straight from O^T in TMEM (this thread: value
 // column vcol), 16 rows at a time, rows >= len skipped.
-__device__ __forceinline__ void fscan_store_tail(uint32_t tl_o, int len, int tok0, int H, int h, int ib, int quad,
-                                                 int lane, bf16* tst, bf16* __restrict__ o) {
+__device__ __forceinline__ void fscan_store_tail(uint32_t tl_o, int len, int tok0, int H, int V, int h, int ib,
+                                                 int quad, int lane, bf16* tst, bf16* __restrict__ o) {
+    const int wcols = V - 32 * quad;   // value columns of this warp's 32 that o has
+    if (wcols <= 0) return;
 #pragma unroll 1
     for (int cq = 0; cq < 32; cq += 16) {
         const int r0 = ib + cq;
@@ -582,8 +586,8 @@ __device__ __forceinline__ void fscan_store_tail(uint32_t tl_o, int len, int tok
             float ov[16];
             tc::tmem_ld16(tl_o + r0, ov);
             tc::tmem_wait_ld();
-            tc::warp_store_t16(tst, ov, o + ((size_t)(tok0 + r0) * H + h) * D + 32 * quad, (size_t)H * D, len - r0,
-                               lane);
+            tc::warp_store_t16(tst, ov, o + ((size_t)(tok0 + r0) * H + h) * V + 32 * quad, (size_t)H * V, len - r0,
+                               lane, wcols);
         }
     }
 }
@@ -616,7 +620,8 @@ __device__ __forceinline__ void fscan_compute(const Shape& s, const float* __res
     const int H = s.H;
     const int vcol = 32 * quad + lane;  // TMEM lane and value column of this thread
     const uint32_t tl = tc::taddr(tb, 32 * quad, 0);
-    const size_t st_off = ((size_t)nseq * H + h) * D * D;
+    const int K = s.K, V = s.V;         // the state's widths ([K][V] per sequence and head; K, V <= D)
+    const size_t st_off = ((size_t)nseq * H + h) * K * V;
     uint64_t* ufull = bar + 7;          // the U tile of the current chunk has landed
     const int kb = 64 * half;   // this thread's half of the key columns of S^T
     const int ib = 32 * half;   // this thread's half of the chunk rows
@@ -626,7 +631,8 @@ __device__ __forceinline__ void fscan_compute(const Shape& s, const float* __res
     for (int cb = kb; cb < kb + 64; cb += 16) {
         float a[16];
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj) a[jj] = h0 ? h0[st_off + (size_t)(cb + jj) * D + vcol] : 0.f;
+        for (int jj = 0; jj < 16; ++jj)
+            a[jj] = (h0 && cb + jj < K && vcol < V) ? h0[st_off + (size_t)(cb + jj) * V + vcol] : 0.f;
         tc::tmem_st16(tl + cb, a);
     }
     tc::tmem_wait_st();
@@ -720,7 +726,7 @@ __device__ __forceinline__ void fscan_compute(const Shape& s, const float* __res
             if ((MODE & 1) && lenp == BT)
                 fscan_stage_out(to, reinterpret_cast<bf16*>(base + ScanMap<MODE>::OST) + ((it - 1) & 1) * BT * D, ib, vcol);
             else
-                fscan_store_tail(to, lenp, tok0p, H, h, ib, quad, lane, tst, o);
+                fscan_store_tail(to, lenp, tok0p, H, s.V, h, ib, quad, lane, tst, o);
         }
         if (MODE & 2) {
             // R and S (from the bf16 S^T operand still in TMEM) as tile images into their staging
@@ -756,7 +762,7 @@ __device__ __forceinline__ void fscan_compute(const Shape& s, const float* __res
             if ((MODE & 1) && lenp == BT)
                 fscan_stage_out(to, reinterpret_cast<bf16*>(base + ScanMap<MODE>::OST) + (last & 1) * BT * D, ib, vcol);
             else
-                fscan_store_tail(to, lenp, tok0p, H, h, ib, quad, lane, tst, o);
+                fscan_store_tail(to, lenp, tok0p, H, s.V, h, ib, quad, lane, tst, o);
         }
     }
     if (ok && ht) {
@@ -766,7 +772,8 @@ __device__ __forceinline__ void fscan_compute(const Shape& s, const float* __res
             tc::tmem_ld16(tl + cb, a);
             tc::tmem_wait_ld();
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) ht[st_off + (size_t)(cb + jj) * D + vcol] = a[jj];
+            for (int jj = 0; jj < 16; ++jj)
+                if (cb + jj < K && vcol < V) ht[st_off + (size_t)(cb + jj) * V + vcol] = a[jj];
         }
     }
 }
@@ -822,7 +829,7 @@ __device__ __forceinline__ void fscan_issue(const Shape& s, const Table& t, cons
         }
         // the output of chunk c-2 (a full chunk), staged by the compute warps during chunk c-1
         const bool o_out = (MODE & 1) && it >= 2 && pl == BT;
-        if (o_out) fscan_tma_out(tmo, sb + ScanMap<MODE>::OST + (it & 1) * BT * D * 2, pt, h, lane);
+        if (o_out) fscan_tma_out(tmo, sb + ScanMap<MODE>::OST + (it & 1) * BT * D * 2, pt, h, s.V, lane);
         if ((MODE & 1) && it >= 1) {   // extent of chunk c-1, whose output is stored next iteration
             pl = __ldg(t.chunk_len + c - 1);
             pt = __ldg(t.chunk_tok0 + c - 1);
@@ -928,9 +935,9 @@ __global__ void __launch_bounds__(ST_ALL, 1)
     if ((MODE & 1) && issuer && c1 > c0) {
         const int last = c1 - 1 - c0, lane = tid & 31;
         constexpr int OST = ScanMap<MODE>::OST;
-        if (last >= 1 && pl == BT) fscan_tma_out(&tmo, sb + OST + ((last - 1) & 1) * BT * D * 2, pt, h, lane);
+        if (last >= 1 && pl == BT) fscan_tma_out(&tmo, sb + OST + ((last - 1) & 1) * BT * D * 2, pt, h, s.V, lane);
         if (t.chunk_len[c1 - 1] == BT)
-            fscan_tma_out(&tmo, sb + OST + (last & 1) * BT * D * 2, t.chunk_tok0[c1 - 1], h, lane);
+            fscan_tma_out(&tmo, sb + OST + (last & 1) * BT * D * 2, t.chunk_tok0[c1 - 1], h, s.V, lane);
         if (lane == 0) tc::bulk_wait_all();
     }
     if (warp == 0) tc::tmem_dealloc(tb, 512);
@@ -945,8 +952,9 @@ cudaError_t run_prep(const Shape& s, const void* q, const void* k, const void* v
     if (e != cudaSuccess) return e;
     CUtensorMap mq, mk, mv, mg;
     memset(&mg, 0, sizeof(mg));
-    if (!tmap_rows_bf16(&mq, q, s.Ttot, s.H, D) || !tmap_rows_bf16(&mk, k, s.Ttot, s.H, D) ||
-        !tmap_rows_bf16(&mv, v, s.Ttot, s.H, D) || (GATE == 2 && !tmap_rows_f32(&mg, g, s.Ttot, s.H, D)))
+    // the inputs at their own widths K, V (<= D): the boxes' columns past them read as zeros
+    if (!tmap_rows_bf16(&mq, q, s.Ttot, s.H, s.K) || !tmap_rows_bf16(&mk, k, s.Ttot, s.H, s.K) ||
+        !tmap_rows_bf16(&mv, v, s.Ttot, s.H, s.V) || (GATE == 2 && !tmap_rows_f32(&mg, g, s.Ttot, s.H, s.K, D)))
         return cudaErrorInvalidValue;
     dim3 grid(s.NC, s.H);
     k_prep_tc<GATE, BWD, GD2><<<grid, PT, PREP_SMEM, st>>>(s, mq, mk, mv, mg, (const bf16*)beta, g, t, f, gd);
@@ -959,7 +967,7 @@ cudaError_t run_scan(const Shape& s, const float* h0, Table t, FwdTC f, void* o,
     if (e != cudaSuccess) return e;
     CUtensorMap mo;
     memset(&mo, 0, sizeof(mo));
-    if ((MODE & 1) && !tmap_rows_bf16(&mo, o, s.Ttot, s.H, D)) return cudaErrorInvalidValue;
+    if ((MODE & 1) && !tmap_rows_bf16(&mo, o, s.Ttot, s.H, s.V)) return cudaErrorInvalidValue;
     dim3 grid(s.N, s.H);
     k_fwd_scan_tc<MODE><<<grid, ST_ALL, ScanMap<MODE>::SMEM, st>>>(s, mo, h0, t, f, (bf16*)o, ht);
     return cudaGetLastError();

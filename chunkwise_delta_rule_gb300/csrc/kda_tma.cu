@@ -1,4 +1,5 @@
-// Host side of the TMA tensor maps for the token-major inputs [Ttot][H][D].
+// Host side of the TMA tensor maps for the token-major inputs [Ttot][H][D]. A box may be wider
+// than the tensor's rows: the columns past D read as zeros (loads) or are dropped (stores).
 // The encode function is taken from the driver through the runtime's
 // versioned entry-point query, so the library does not link the driver API.
 #include <cudaTypedefs.h>
@@ -41,8 +42,9 @@ bool tmap_rows_bf16(CUtensorMap* m, const void* base, int Ttot, int H, int D) {
     return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, Ttot, H, D, 64, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-bool tmap_rows_f32(CUtensorMap* m, const void* base, int Ttot, int H, int D) {
-    return encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, Ttot, H, D, D, CU_TENSOR_MAP_SWIZZLE_NONE);
+bool tmap_rows_f32(CUtensorMap* m, const void* base, int Ttot, int H, int D, int box_x) {
+    return encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, Ttot, H, D, box_x > 0 ? box_x : D,
+                  CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 }  // namespace kda

@@ -387,15 +387,16 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 // row t, a[0..15]). Writes its transpose, dst[c * ld + t] for c < ncols rows
 // of the destination, as 16-byte stores through a per-warp staging tile of
 // 16 x 40 bf16.
+// wcols: columns of the 32 that exist in dst (a multiple of 8; 32 for a full block).
 __device__ __forceinline__ void warp_store_t16(__nv_bfloat16* stg, const float (&a)[16], __nv_bfloat16* dst,
-                                               size_t ld, int ncols, int lane) {
+                                               size_t ld, int ncols, int lane, int wcols = 32) {
 #pragma unroll
     for (int j = 0; j < 16; ++j) stg[j * 40 + lane] = __float2bfloat16_rn(a[j]);
     __syncwarp();
 #pragma unroll
     for (int p = lane; p < 64; p += 32) {
         const int r = p >> 2, q = p & 3;
-        if (r < ncols)
+        if (r < ncols && q * 8 < wcols)
             *reinterpret_cast<uint4*>(dst + (size_t)r * ld + q * 8) = *reinterpret_cast<const uint4*>(stg + r * 40 + q * 8);
     }
     __syncwarp();
@@ -434,15 +435,15 @@ __device__ __forceinline__ void warp_store_t16_img(__nv_bfloat16* stg, const flo
 
 // A warp holds 8 values per lane (lane t: column t of rows 0..7 of a 8 x 32
 // block, e.g. one key per lane and 8 tokens). Writes the block as 8 rows of 32
-// bf16, dst[r * ld + t] for r < nrows, through a dense per-warp staging tile of
-// 8 x 32 bf16 (512 bytes): one 16-byte store per lane.
+// bf16, dst[r * ld + t] for r < nrows and t < wcols (a multiple of 8), through a
+// dense per-warp staging tile of 8 x 32 bf16 (512 bytes): one 16-byte store per lane.
 __device__ __forceinline__ void warp_store_t8(__nv_bfloat16* stg, const float (&a)[8], __nv_bfloat16* dst,
-                                              size_t ld, int nrows, int lane) {
+                                              size_t ld, int nrows, int lane, int wcols = 32) {
 #pragma unroll
     for (int r = 0; r < 8; ++r) stg[r * 32 + lane] = __float2bfloat16_rn(a[r]);
     __syncwarp();
     const int r = lane >> 2, q = lane & 3;
-    if (r < nrows)
+    if (r < nrows && q * 8 < wcols)
         *reinterpret_cast<uint4*>(dst + (size_t)r * ld + q * 8) = *reinterpret_cast<const uint4*>(stg + r * 32 + q * 8);
     __syncwarp();
 }

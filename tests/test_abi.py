@@ -200,7 +200,12 @@ def test_unequal_widths_pad_to_the_working_width():
         return (x + 255) // 256 * 256
 
     lib = _lib.load()
-    p = _prob(K=80, V=112)              # bf16, channel gate, B=2, T=130, H=3: runs at 128
+    # bf16 widths that are multiples of 8 run on the tensor cores as they are: the 128-wide path's
+    # workspace and no padded copies
+    assert _ws(_prob(K=80, V=112), 0) == _ws(_prob(K=128, V=128), 0)
+    # backward: the two state-adjoint hand-over buffers of the time pieces hold [K][V] states
+    assert _ws(_prob(K=80, V=112), 1) == _ws(_prob(K=128, V=128), 1) - 2 * (up(4 * 2 * 3 * 128 * 128) - up(4 * 2 * 3 * 80 * 112))
+    p = _prob(K=84, V=116)              # bf16, channel gate, B=2, T=130, H=3: padded to 128
     work = _prob(K=128, V=128)
     T, H, D = 2 * 130, 3, 128
     # q, k, v, g (fp32), o, ht (fp32) at the working width
@@ -210,9 +215,11 @@ def test_unequal_widths_pad_to_the_working_width():
     pad_b = pad_f + up(2 * T * H * D) + up(4 * 2 * H * D * D) + 3 * up(2 * T * H * D) + up(4 * T * H * D) \
         + up(4 * 2 * H * D * D)
     assert _ws(p, 1) == _ws(work, 1) + pad_b
-    # bf16 widths up to 128 all run at 128 (the tensor-core width), fp32 ones within 64 at 64
-    assert _ws(_prob(K=32, V=48), 0) == _ws(p, 0)
-    assert _ws(_prob(K=64, V=64), 0) == _ws(p, 0)
+    # bf16 widths up to 128 all run at 128 (the tensor-core width; 32/48 and 64/64 unpadded, 36/44
+    # padded), fp32 ones within 64 at 64
+    assert _ws(_prob(K=32, V=48), 0) == _ws(work, 0)
+    assert _ws(_prob(K=64, V=64), 0) == _ws(work, 0)
+    assert _ws(_prob(K=36, V=44), 0) == _ws(p, 0)
     D = 64
     pad64 = 3 * up(4 * T * H * D) + up(4 * T * H * D) + up(4 * T * H * D) + up(4 * 2 * H * D * D)
     assert _ws(_prob(K=32, V=48, io=1), 0) == _ws(_prob(K=64, V=64, io=1), 0) + pad64

@@ -180,3 +180,50 @@ def test_wide_keys_saved_equals_recomputed():
     for a, b in zip(*out):
         if a is not None:
             assert torch.equal(a, b)
+
+
+# bf16 widths that are multiples of 8 run on the tensor cores at their own widths (the tensor maps
+# read the missing columns as zeros; the state, tail outputs, gradients and GatedDeltaNet-2 vectors
+# are read and written at K and V); other bf16 widths are padded to 128
+@pytest.mark.parametrize("gate,K,V", [("channel", 96, 48), ("scalar", 40, 120), ("channel", 36, 44)])
+def test_native_and_padded_bf16_widths(gate, K, V):
+    case = width_case("bf16", gate, 2, 150, 2, K, V, 112)
+    got, ref = run_both(case)
+    compare(case, got, ref, 1, TOL["bf16"])
+
+
+def test_native_widths_gdn2_and_strong_decay():
+    case = width_case("bf16", "channel", 1, 150, 2, 80, 112, 113)
+    got, ref = run_both(case, gdn2=True)
+    compare(case, got, ref, 1, TOL["bf16"])
+    case = make_case(io="bf16", gate="channel", B=1, T=200, H=2, K=80, V=48, seed=114, g_shift=-4.0, g_min=-8.0)
+    G = torch.cumsum(case.g.double(), dim=1) / np.log(2.0)
+    assert float((G[:, :64].max(dim=1).values - G[:, :64].min(dim=1).values).max()) > 80
+    got, ref = run_both(case)
+    compare(case, got, ref, 1, TOL["bf16"])
+
+
+def test_native_widths_backward_schedules_agree_bitwise():
+    """Joint, time pieces and one pass hand the state adjoint over at [K][V] (80 x 112 here)."""
+    import chunkwise_delta_rule_gb300 as kda
+    case = width_case("bf16", "channel", 2, 640, 2, 80, 112, 115)
+    c = case.to("cuda")
+    outs = []
+    for sched in (1, 3, 9):
+        p = kda.make_problem(c.q, c.k, c.v, c.g, c.beta, gate="channel", scale=case.scale, initial_state=c.h0,
+                             save_policy=1, schedule=sched)
+        o, ht, sv = kda.kda_chunk_fwd(p)
+        outs.append((o, ht) + tuple(kda.kda_chunk_bwd(p, c.do, c.dht, saved=sv)))
+    torch.cuda.synchronize()
+    for other in outs[1:]:
+        for a, b in zip(outs[0], other):
+            if a is not None:
+                assert torch.equal(a, b)
+    got = dict(o=outs[0][0], ht=outs[0][1], dq=outs[0][2], dk=outs[0][3], dv=outs[0][4], dg=outs[0][5],
+               dbeta=outs[0][6], dh0=outs[0][7])
+    p = packed(case)
+    ref = run_oracle_prologue_arrays(p["q"], p["k"], p["v"], p["beta"], p["g"], A_log=None, dt_bias=None,
+                                     lower_bound=0.0, eps=1e-6, scale=case.scale, gate=case.gate,
+                                     seq_starts=case.seq_starts, h0=p["h0"], do=p["do"], dht=p["dht"],
+                                     qk_norm=False, erase=None, write=None)
+    compare(case, got, ref, 1, TOL["bf16"])
