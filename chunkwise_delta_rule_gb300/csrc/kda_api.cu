@@ -206,6 +206,7 @@ kda::Shape shape_of(const kda_problem* p, const Dims& d) {
     s.NC = d.NC;
     s.Ttot = d.Ttot;
     s.scale = p->scale > 0.f ? p->scale : 1.0f / sqrtf((float)p->K);
+    s.Hq = s.Hg = p->H;   // one q, k and one g, beta, erase head per value head
     return s;
 }
 
@@ -290,8 +291,11 @@ kda_problem pad_inner(const kda_problem* p, const PadBufs* b) {
 }
 
 // Grouped value heads: the problem the rest of the library sees has one key head per value
-// head (q, k expanded in the workspace).
+// head. On the tensor-core path without the prologue its kernels read q, k of key head j / G
+// for value head j in place; otherwise q, k are first copied per value head into the workspace.
 bool gva(const kda_problem* p) { return p->HV != 0 && p->HV != p->H; }
+bool has_prologue(const kda_problem* p);
+bool gva_in_place(const kda_problem* p) { return use_tc(p) && !has_prologue(p); }
 kda_problem gva_inner(const kda_problem* p, const void* qx, const void* kx) {
     kda_problem c = *p;
     c.H = p->HV;
@@ -302,7 +306,8 @@ kda_problem gva_inner(const kda_problem* p, const void* qx, const void* kx) {
 }
 size_t gva_bytes(const kda_problem* p, const Dims& d, bool bwd) {
     const size_t one = up((size_t)(p->io == KDA_BF16 ? 2 : 4) * d.Ttot * p->HV * d.D);
-    return one * (bwd ? 4 : 2);   // q, k copies (and, backward, their gradients)
+    // q, k copies unless read in place; backward, their gradients per value head
+    return one * ((gva_in_place(p) ? 0 : 2) + (bwd ? 2 : 0));
 }
 
 // Value widths above the block width M (128, or 256 when K > 128): NB = ceil(V / M) value blocks
@@ -317,6 +322,14 @@ int vblocks(const kda_problem* p) {
 int vblock_width(const kda_problem* p) { return (p->V + vblocks(p) - 1) / vblocks(p); }
 bool vsplit(const kda_problem* p) { return vblocks(p) > 1; }
 long long heads_v(const kda_problem* p) { return p->HV ? p->HV : p->H; }
+struct SplitBufs;
+kda_problem split_inner(const kda_problem* p, const SplitBufs* b);
+// The blocks read g, beta and erase in place (block value head j reads head j / NB) when they run on
+// the tensor-core path at their own width without the prologue; otherwise those repeat per block.
+bool split_in_place(const kda_problem* p) {
+    const kda_problem in = split_inner(p, nullptr);
+    return use_tc(&in) && !has_prologue(p) && pad_width(&in) == 0;
+}
 // channels of g (and dt_bias) per token and head
 int gate_width(const kda_problem* p) { return p->gate == KDA_GATE_NONE ? 0 : (p->gate == KDA_GATE_CHANNEL ? p->K : 1); }
 struct SplitBufs {
@@ -328,7 +341,7 @@ struct SplitBufs {
 size_t split_layout(const kda_problem* p, const Dims& d, bool bwd, char* base, SplitBufs& b) {
     const size_t NB = vblocks(p), Vp = NB * vblock_width(p), es = p->io == KDA_BF16 ? 2 : 4;
     const size_t Hv = heads_v(p), T = d.Ttot, N = d.N, K = p->K, gw = gate_width(p);
-    const bool padv = Vp != (size_t)p->V, gd2 = p->erase != nullptr;
+    const bool padv = Vp != (size_t)p->V, gd2 = p->erase != nullptr, inpl = split_in_place(p);
     size_t n = 0;
     auto take = [&](size_t bytes) -> char* {
         char* r = base ? base + n : nullptr;
@@ -340,9 +353,11 @@ size_t split_layout(const kda_problem* p, const Dims& d, bool bwd, char* base, S
         if (gd2) b.write = take(es * T * Hv * Vp);
         b.o = take(es * T * Hv * Vp);
     }
-    if (!gd2) b.beta = take(es * T * Hv * NB);
-    if (gd2) b.erase = take(es * T * Hv * NB * K);
-    if (gw) b.g = reinterpret_cast<float*>(take(4 * T * Hv * NB * gw));
+    if (!inpl) {
+        if (!gd2) b.beta = take(es * T * Hv * NB);
+        if (gd2) b.erase = take(es * T * Hv * NB * K);
+        if (gw) b.g = reinterpret_cast<float*>(take(4 * T * Hv * NB * gw));
+    }
     if (p->A_log) b.A_log = reinterpret_cast<float*>(take(4 * Hv * NB));
     if (p->dt_bias) b.dtb = reinterpret_cast<float*>(take(4 * Hv * NB * gw));
     if (p->h0) b.h0 = reinterpret_cast<float*>(take(4 * N * Hv * K * Vp));
@@ -603,9 +618,15 @@ size_t kda_saved_size(const kda_problem* p) {
     return use_tc(p) ? L.ftc + L.ftc_b : L.fcore + L.fextra;
 }
 
+// Value heads per head of q, k (Gq) and of g, beta, erase (Gg) for the tensor-core kernels' in-place
+// reads of grouped heads and value blocks (1, 1: every input has one head per value head).
+struct HeadGroups {
+    int Gq = 1, Gg = 1;
+};
+
 // The chunk pipeline proper (the prologue, if any, has already run).
 static kda_status chunk_fwd_core(const kda_problem* p, void* o, float* ht, void* saved, void* ws,
-                                 size_t ws_bytes, kda_stream_t stream) {
+                                 size_t ws_bytes, kda_stream_t stream, HeadGroups hgr = {}) {
     Dims d;
     kda_status st = check_dims(p, d);
     if (st != KDA_OK) return st;
@@ -623,7 +644,13 @@ static kda_status chunk_fwd_core(const kda_problem* p, void* o, float* ht, void*
     if ((st = check_ws(ws, ws_bytes, kda_workspace_size(p, 0))) != KDA_OK) return st;
     if (p->save_policy && (st = check_ws(saved, kda_saved_size(p), kda_saved_size(p))) != KDA_OK)
         return fail(KDA_ERR_WORKSPACE, "saved buffer: " + g_err);
-    const kda::Shape s = shape_of(p, d);
+    if ((hgr.Gq != 1 || hgr.Gg != 1) && !use_tc(p))
+        return fail(KDA_ERR_INVALID_ARG, "grouped inputs read in place need the tensor-core path");
+    kda::Shape s = shape_of(p, d);
+    s.Gq = hgr.Gq;
+    s.Gg = hgr.Gg;
+    s.Hq = s.H / hgr.Gq;
+    s.Hg = s.H / hgr.Gg;
     Carver cw{static_cast<char*>(ws)};
     kda::Table t = carve_table(cw, d);
     const int bf16 = p->io == KDA_BF16;
@@ -672,7 +699,7 @@ static kda_status chunk_fwd_core(const kda_problem* p, void* o, float* ht, void*
 
 static kda_status chunk_bwd_core(const kda_problem* p, const void* dout, const float* dht, const void* saved,
                                  void* dq, void* dk, void* dv, float* dg, void* dbeta, void* derase, void* dwrite,
-                                 float* dh0, void* ws, size_t ws_bytes, kda_stream_t stream) {
+                                 float* dh0, void* ws, size_t ws_bytes, kda_stream_t stream, HeadGroups hgr = {}) {
     Dims d;
     kda_status st = check_dims(p, d);
     if (st != KDA_OK) return st;
@@ -700,7 +727,13 @@ static kda_status chunk_bwd_core(const kda_problem* p, const void* dout, const f
         if (reinterpret_cast<uintptr_t>(saved) % ALIGN)
             return fail(KDA_ERR_WORKSPACE, "saved buffer not 256-byte aligned");
     }
-    const kda::Shape s = shape_of(p, d);
+    if ((hgr.Gq != 1 || hgr.Gg != 1) && !use_tc(p))
+        return fail(KDA_ERR_INVALID_ARG, "grouped inputs read in place need the tensor-core path");
+    kda::Shape s = shape_of(p, d);
+    s.Gq = hgr.Gq;
+    s.Gg = hgr.Gg;
+    s.Hq = s.H / hgr.Gq;
+    s.Hg = s.H / hgr.Gg;
     Carver cw{static_cast<char*>(ws)};
     kda::Table t = carve_table(cw, d);
     if (use_tc(p)) {
@@ -939,8 +972,9 @@ static kda_status gva_expand(const kda_problem* p, const Dims& d, char* w, kda_p
     return e == cudaSuccess ? KDA_OK : cuda_fail(e, "grouped heads: expand q, k");
 }
 
+// Gg > 1: the value-block caller's g, beta and erase, read in place (value head j reads head j / Gg).
 static kda_status chunk_fwd_gva(const kda_problem* p, void* o, float* ht, void* saved, void* ws, size_t ws_bytes,
-                                kda_stream_t stream) {
+                                kda_stream_t stream, int Gg = 1) {
     if (!p || !gva(p)) return chunk_fwd_pro(p, o, ht, saved, ws, ws_bytes, stream);
     Dims d;
     kda_status st = check_dims(p, d);
@@ -950,6 +984,8 @@ static kda_status chunk_fwd_gva(const kda_problem* p, void* o, float* ht, void* 
     if (d.Ttot == 0) return chunk_fwd_pro(&in, o, ht, saved, ws, ws_bytes, stream);
     const size_t core = kda_workspace_size(&in, 0);
     if ((st = check_ws(ws, ws_bytes, core + gva_bytes(p, d, false))) != KDA_OK) return st;
+    if (gva_in_place(p)) return chunk_fwd_core(&in, o, ht, saved, ws, core, stream, HeadGroups{p->HV / p->H, Gg});
+    if (Gg != 1) return fail(KDA_ERR_INVALID_ARG, "value blocks read in place need grouped heads read in place");
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     if ((st = gva_expand(p, d, static_cast<char*>(ws) + core, in, cs)) != KDA_OK) return st;
     return chunk_fwd_pro(&in, o, ht, saved, ws, core, stream);
@@ -957,7 +993,8 @@ static kda_status chunk_fwd_gva(const kda_problem* p, void* o, float* ht, void* 
 
 static kda_status chunk_bwd_gva(const kda_problem* p, const void* dout, const float* dht, const void* saved, void* dq,
                                 void* dk, void* dv, float* dg, void* dbeta, void* derase, void* dwrite, float* dh0,
-                                float* dA_log, float* ddt_bias, void* ws, size_t ws_bytes, kda_stream_t stream) {
+                                float* dA_log, float* ddt_bias, void* ws, size_t ws_bytes, kda_stream_t stream,
+                                int Gg = 1) {
     if (!p || !gva(p))
         return chunk_bwd_pro(p, dout, dht, saved, dq, dk, dv, dg, dbeta, derase, dwrite, dh0, dA_log, ddt_bias, ws,
                              ws_bytes, stream);
@@ -974,12 +1011,18 @@ static kda_status chunk_bwd_gva(const kda_problem* p, const void* dout, const fl
     if ((st = check_ws(ws, ws_bytes, core + gva_bytes(p, d, true))) != KDA_OK) return st;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     char* w = static_cast<char*>(ws) + core;
-    if ((st = gva_expand(p, d, w, in, cs)) != KDA_OK) return st;
     const size_t one = up((size_t)(p->io == KDA_BF16 ? 2 : 4) * d.Ttot * p->HV * d.D);
-    void* dqx = w + 2 * one;
-    void* dkx = w + 3 * one;
-    st = chunk_bwd_pro(&in, dout, dht, saved, dqx, dkx, dv, dg, dbeta, derase, dwrite, dh0, dA_log, ddt_bias, ws, core,
-                       stream);
+    const bool inpl = gva_in_place(p);
+    if (!inpl && Gg != 1) return fail(KDA_ERR_INVALID_ARG, "value blocks read in place need grouped heads read in place");
+    if (!inpl && (st = gva_expand(p, d, w, in, cs)) != KDA_OK) return st;
+    void* dqx = w + (inpl ? 0 : 2) * one;   // dq, dk per value head, after the q, k copies if any
+    void* dkx = w + (inpl ? 1 : 3) * one;
+    if (inpl)
+        st = chunk_bwd_core(&in, dout, dht, saved, dqx, dkx, dv, dg, dbeta, derase, dwrite, dh0, ws, core, stream,
+                            HeadGroups{p->HV / p->H, Gg});
+    else
+        st = chunk_bwd_pro(&in, dout, dht, saved, dqx, dkx, dv, dg, dbeta, derase, dwrite, dh0, dA_log, ddt_bias, ws,
+                           core, stream);
     if (st != KDA_OK) return st;
     cudaError_t e = traced("k_gva_reduce", cs, [&] {
         return kda::launch_gva_reduce(d.Ttot, p->H, p->HV / p->H, d.D, p->io == KDA_BF16, dqx, dkx, dq, dk, cs);
@@ -1172,7 +1215,10 @@ kda_status kda_chunk_fwd(const kda_problem* p, void* o, float* ht, void* saved, 
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     if ((st = split_inputs(p, d, b, cs)) != KDA_OK) return st;
     const kda_problem in = split_inner(p, &b);
-    if ((st = chunk_fwd_pad(&in, b.o ? b.o : o, b.ht, saved, ws, core, stream)) != KDA_OK) return st;
+    // in place: the blocks run at their own width, so the padding layer has nothing to do
+    st = split_in_place(p) ? chunk_fwd_gva(&in, b.o ? b.o : o, b.ht, saved, ws, core, stream, vblocks(p))
+                           : chunk_fwd_pad(&in, b.o ? b.o : o, b.ht, saved, ws, core, stream);
+    if (st != KDA_OK) return st;
     SplitIo io{p, d, cs};
     io.value_rows(false, p->io == KDA_BF16 ? 2 : 4, b.o, o);
     io.states(false, b.ht, ht);
@@ -1211,8 +1257,13 @@ kda_status kda_chunk_bwd(const kda_problem* p, const void* dout, const float* dh
     io.states(true, dht, b.dht);
     if (io.e != cudaSuccess) return cuda_fail(io.e, "split into value blocks");
     const kda_problem in = split_inner(p, &b);
-    st = chunk_bwd_pad(&in, b.dout ? b.dout : dout, dht ? b.dht : nullptr, saved, dq, dk, b.dv ? b.dv : dv, b.dg,
-                       b.dbeta, b.derase, b.dwrite ? b.dwrite : dwrite, b.dh0, b.dA, b.ddtb, ws, core, stream);
+    if (split_in_place(p))
+        st = chunk_bwd_gva(&in, b.dout ? b.dout : dout, dht ? b.dht : nullptr, saved, dq, dk, b.dv ? b.dv : dv, b.dg,
+                           b.dbeta, b.derase, b.dwrite ? b.dwrite : dwrite, b.dh0, b.dA, b.ddtb, ws, core, stream,
+                           vblocks(p));
+    else
+        st = chunk_bwd_pad(&in, b.dout ? b.dout : dout, dht ? b.dht : nullptr, saved, dq, dk, b.dv ? b.dv : dv, b.dg,
+                           b.dbeta, b.derase, b.dwrite ? b.dwrite : dwrite, b.dh0, b.dA, b.ddtb, ws, core, stream);
     if (st != KDA_OK) return st;
     const long long Hv = heads_v(p);
     io.value_rows(false, es, b.dv, dv);

@@ -100,7 +100,7 @@ __device__ __forceinline__ void dstate_chunk(int c, int h, const Shape& s, const
                 const int r = warp + i * (NTHREADS / 32);
                 if (r < len) {
                     const size_t tok = (size_t)(tok0 + r) * H + h;
-                    const float bt = wr ? 0.f : ld(beta + tok);
+                    const float bt = wr ? 0.f : ld(beta + (size_t)(tok0 + r) * heads_g(s) + h / s.Gg);
                     for (int cc = lane; cc < DC; cc += 32) {
                         const int col = v0 + cc;
                         if (col >= Vw) break;
@@ -235,11 +235,13 @@ __device__ __forceinline__ void intra_chunk(int c, int h, const Shape& s, const 
         tile_copy<BT, BT>([&](int r, int cc) { return ldg(HQ + r * BT + cc); },
                           [&](int r, int cc, float x) { sHQ[r * LA + cc] = x; });
     }
-    if (tid < BT) sBeta[tid] = (tid < len && !gd.erase) ? ldg(beta + (size_t)(tok0 + tid) * H + h) : 0.f;
+    // heads of q, k and of g, beta, erase (value head h reads q, k of head h / Gq, the rest of h / Gg)
+    const int hq = h / s.Gq, Hq = heads_q(s), hg = h / s.Gg, Hg = heads_g(s);
+    if (tid < BT) sBeta[tid] = (tid < len && !gd.erase) ? ldg(beta + (size_t)(tok0 + tid) * Hg + hg) : 0.f;
     // GatedDeltaNet-2: the erase vector takes beta's place on the key side (E = b .* K exp(G))
     const TI* er = static_cast<const TI*>(gd.erase);
     auto ebeta = [&](int r, int gcol) {
-        return er ? ((r < len && gcol < Kw) ? ld(er + ((size_t)(tok0 + r) * H + h) * Kw + gcol) : 0.f) : sBeta[r];
+        return er ? ((r < len && gcol < Kw) ? ld(er + ((size_t)(tok0 + r) * Hg + hg) * Kw + gcol) : 0.f) : sBeta[r];
     };
     const float* QS = b.QS + ch * BT * D;
     const float* PS = b.PS + ch * BT * D;
@@ -253,16 +255,17 @@ __device__ __forceinline__ void intra_chunk(int c, int h, const Shape& s, const 
     for (int cb = 0; cb < NB; ++cb) {
         const int c0 = cb * DC;
         if (cb > 0) __syncthreads();   // the previous block's tiles are no longer read
-        auto off = [&](int r, int col) { return ((size_t)(tok0 + r) * H + h) * Kw + c0 + col; };
-        tile_copy<BT, DC>([&](int r, int col) { return (r < len && c0 + col < Kw) ? ldg(k + off(r, col)) : 0.f; },
+        auto offq = [&](int r, int col) { return ((size_t)(tok0 + r) * Hq + hq) * Kw + c0 + col; };
+        auto offg = [&](int r, int col) { return ((size_t)(tok0 + r) * Hg + hg) * Kw + c0 + col; };
+        tile_copy<BT, DC>([&](int r, int col) { return (r < len && c0 + col < Kw) ? ldg(k + offq(r, col)) : 0.f; },
                           [&](int r, int col, float x) { sK[r * LD + col] = x; });
-        tile_copy<BT, DC>([&](int r, int col) { return (r < len && c0 + col < Kw) ? ldg(q + off(r, col)) : 0.f; },
+        tile_copy<BT, DC>([&](int r, int col) { return (r < len && c0 + col < Kw) ? ldg(q + offq(r, col)) : 0.f; },
                           [&](int r, int col, float x) { sQ[r * LD + col] = x; });
         tile_copy<BT, DC>(
             [&](int r, int col) {
                 if (GATE == 0 || r >= len) return 0.f;
-                if (GATE == 2) return c0 + col < Kw ? ldg(g + off(r, col)) * LOG2E : 0.f;
-                return ldg(g + (size_t)(tok0 + r) * H + h) * LOG2E;
+                if (GATE == 2) return c0 + col < Kw ? ldg(g + offg(r, col)) * LOG2E : 0.f;
+                return ldg(g + (size_t)(tok0 + r) * Hg + hg) * LOG2E;
             },
             [&](int r, int col, float x) { sG[r * LD + col] = x; });
         __syncthreads();

@@ -107,12 +107,21 @@ struct BwdTC {
 constexpr float PREP_RANGE_LOG2 = 80.0f;
 
 struct Shape {
-    int H, K, V;
+    int H, K, V;  // H: value heads (one state each)
     int N;        // sequences
     int NC;       // chunk slots (upper bound)
     int Ttot;     // tokens on the packed axis
     float scale;
+    // Value heads per head of q, k (Gq) and per head of g, beta, erase (Gg): value head h reads
+    // q, k of head h / Gq and g, beta, erase of head h / Gg, so grouped heads and value blocks
+    // read those inputs in place (1 and 1 on every path but the tensor-core one). Hq = H / Gq and
+    // Hg = H / Gg are the head counts of those rows, set with them (kernel parameters, so no
+    // register holds them).
+    int Gq = 1, Gg = 1, Hq = 0, Hg = 0;
 };
+// Head counts of the q, k and of the g, beta, erase rows.
+__host__ __device__ __forceinline__ int heads_q(const Shape& s) { return s.Hq; }
+__host__ __device__ __forceinline__ int heads_g(const Shape& s) { return s.Hg; }
 
 // ---------------------------------------------------------------- element I/O
 __device__ __forceinline__ float ld(const float* p) { return *p; }

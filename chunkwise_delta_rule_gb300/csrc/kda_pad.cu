@@ -1,5 +1,7 @@
-// Unequal or narrower key and value widths: the problem is served at one width
-// D (64 or 128) with every key-side tensor zero-padded from K to D channels and
+// Widths the kernels do not take as they are (bf16 widths that are not multiples
+// of 8, or that the in-operator prologue does not cover; fp32 widths other than
+// 64 or 128; keys above 128): the problem is served
+// at one width D (64, 128 or 256) with every key-side tensor zero-padded from K to D channels and
 // every value-side one from V to D. Padded key channels have k = q = 0, so they
 // neither write nor read the state; padded value columns of the state start at
 // zero and stay zero (their write value and prediction are both zero). The

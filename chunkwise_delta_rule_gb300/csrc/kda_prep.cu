@@ -49,9 +49,10 @@ __device__ __forceinline__ void prep_chunk(int c, int h, const Shape& s, const T
     if (n <= 0) return;
     const int tok0 = t.chunk_tok0[c];
     const int H = s.H;
+    const int hq = h / s.Gq, Hq = heads_q(s), hg = h / s.Gg, Hg = heads_g(s);   // heads of q, k and of g, beta, erase
     const size_t ch = (size_t)c * H + h;
 
-    if (tid < BT) sBeta[tid] = (tid < n && !gd.erase) ? ldg(beta + (size_t)(tok0 + tid) * H + h) : 0.f;
+    if (tid < BT) sBeta[tid] = (tid < n && !gd.erase) ? ldg(beta + (size_t)(tok0 + tid) * Hg + hg) : 0.f;
     // GatedDeltaNet-2: the erase vector takes beta's place on the key rows of E. The token rows of
     // q, k, g and erase are K wide, those of v and write V wide (K = V = D but for the wide chunks
     // of the tensor-core path, whose inputs may be narrower than its 128 columns); columns past
@@ -59,22 +60,23 @@ __device__ __forceinline__ void prep_chunk(int c, int h, const Shape& s, const T
     const int Kw = s.K, Vw = s.V;
     const TI* er = static_cast<const TI*>(gd.erase);
     auto ebeta = [&](int r, int gcol) {
-        return er ? ((r < n && gcol < Kw) ? ld(er + ((size_t)(tok0 + r) * H + h) * Kw + gcol) : 0.f) : sBeta[r];
+        return er ? ((r < n && gcol < Kw) ? ld(er + ((size_t)(tok0 + r) * Hg + hg) * Kw + gcol) : 0.f) : sBeta[r];
     };
     // ---- chunk rows of features c0 .. c0+DC-1 (rows >= n are zero keys/queries
     // and zero decay), then a1: inclusive cumsum down each feature column
     // (padding rows keep G[n-1])
     auto load_block = [&](int c0) {
-        auto off = [&](int r, int col) { return ((size_t)(tok0 + r) * H + h) * Kw + c0 + col; };
-        tile_copy<BT, DC>([&](int r, int col) { return (r < n && c0 + col < Kw) ? ldg(k + off(r, col)) : 0.f; },
+        auto offq = [&](int r, int col) { return ((size_t)(tok0 + r) * Hq + hq) * Kw + c0 + col; };
+        auto offg = [&](int r, int col) { return ((size_t)(tok0 + r) * Hg + hg) * Kw + c0 + col; };
+        tile_copy<BT, DC>([&](int r, int col) { return (r < n && c0 + col < Kw) ? ldg(k + offq(r, col)) : 0.f; },
                           [&](int r, int col, float x) { sK[r * LD + col] = x; });
-        tile_copy<BT, DC>([&](int r, int col) { return (r < n && c0 + col < Kw) ? ldg(q + off(r, col)) : 0.f; },
+        tile_copy<BT, DC>([&](int r, int col) { return (r < n && c0 + col < Kw) ? ldg(q + offq(r, col)) : 0.f; },
                           [&](int r, int col, float x) { sQ[r * LD + col] = x; });
         tile_copy<BT, DC>(
             [&](int r, int col) {
                 if (GATE == 0 || r >= n) return 0.f;
-                if (GATE == 2) return c0 + col < Kw ? ldg(g + off(r, col)) * LOG2E : 0.f;
-                return ldg(g + (size_t)(tok0 + r) * H + h) * LOG2E;
+                if (GATE == 2) return c0 + col < Kw ? ldg(g + offg(r, col)) * LOG2E : 0.f;
+                return ldg(g + (size_t)(tok0 + r) * Hg + hg) * LOG2E;
             },
             [&](int r, int col, float x) { sG[r * LD + col] = x; });
         __syncthreads();

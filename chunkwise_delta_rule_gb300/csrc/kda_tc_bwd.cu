@@ -94,7 +94,8 @@ __device__ __forceinline__ void bscan_fill(uint32_t stg, const FwdTC& f, size_t 
 // Compute warps: per chunk (last to first) S+bar^T -> bf16 A operand, then
 // (while R_bar runs) S_bar^T <- S+bar^T diag(lambda); R_bar^T -> bf16 A operands;
 // then, while the state adjoint update runs, S+bar and the previous P to HBM.
-// NARROW: the states are [K][V] with K, V below D; otherwise [D][D], folded into the addressing.
+// NARROW: the states are [K][V] with K, V taken at run time (at most D); otherwise [D][D], folded into
+// the addressing.
 template <bool NARROW>
 __device__ __forceinline__ void bscan_compute(const Shape& s, const float* __restrict__ dht, const Table& t,
                                               const FwdTC& f, const BwdTC& b, float* __restrict__ dh0,
@@ -526,16 +527,17 @@ __device__ __forceinline__ int cons_find(int& i, int units, const ConsPiece& pc,
     return -1;
 }
 
-// Load group C of unit (h, tok0): k, q by TMA in SW128 rows, g (per-channel gate) as fp32 rows.
+// Load group C from tok0: k, q of head hq by TMA in SW128 rows, g (per-channel gate) of head hg as
+// fp32 rows.
 template <int GATE>
 __device__ __forceinline__ void cons_load_c(uint32_t sb, const CUtensorMap* tmk, const CUtensorMap* tmq,
-                                            const CUtensorMap* tmg, int h, int tok0, uint64_t* b) {
+                                            const CUtensorMap* tmg, int hq, int hg, int tok0, uint64_t* b) {
     tc::mbar_arrive_expect_tx(b, 2 * BT * D * 2 + (GATE == 2 ? BT * D * 4 : 0));
-    tc::tma_load3(sb + C_K, tmk, 0, h, tok0, b);
-    tc::tma_load3(sb + C_K + 8192, tmk, 64, h, tok0, b);
-    tc::tma_load3(sb + C_Q, tmq, 0, h, tok0, b);
-    tc::tma_load3(sb + C_Q + 8192, tmq, 64, h, tok0, b);
-    if (GATE == 2) tc::tma_load3(sb + C_A, tmg, 0, h, tok0, b);
+    tc::tma_load3(sb + C_K, tmk, 0, hq, tok0, b);
+    tc::tma_load3(sb + C_K + 8192, tmk, 64, hq, tok0, b);
+    tc::tma_load3(sb + C_Q, tmq, 0, hq, tok0, b);
+    tc::tma_load3(sb + C_Q + 8192, tmq, 64, hq, tok0, b);
+    if (GATE == 2) tc::tma_load3(sb + C_A, tmg, 0, hg, tok0, b);
 }
 
 // Load group X1 of unit ch: R in rows 0..63 and S in rows 64..191 of each atom column of the
@@ -580,9 +582,11 @@ __device__ __forceinline__ bool cons_wait(uint64_t* b, int& w, int32_t* err) {
 // The consumer loop of one CTA (CT threads): units from the launch's index space until none is left.
 // tb: 512 TMEM columns allocated by the caller. In the joint schedule the X tiles of a unit are loaded
 // once its ready flag is set.
-// NARROW: the token rows of the inputs and gradients are K and V wide (multiples of 8, at most D);
-// otherwise both are D, which the compiler folds into the addressing.
-template <int GATE, bool GD2, bool NARROW>
+// FX (what the addressing takes at run time, the rest folded in by the compiler): 0 = nothing, the
+// token rows D wide and one head of every input per value head; 1 = value head h reads q, k of
+// head h / Gq and g, beta, erase of head h / Gg; 2 = that, and token rows K and V wide (multiples
+// of 8, at most D).
+template <int GATE, bool GD2, int FX>
 __device__ __forceinline__ void cons_body(const Shape& s, const CUtensorMap* tmq_, const CUtensorMap* tmk_,
                                           const CUtensorMap* tmo_, const CUtensorMap* tmg_, const CUtensorMap* tmv_,
                                           const bf16* __restrict__ beta, const float* __restrict__ g, const Table& t,
@@ -591,7 +595,8 @@ __device__ __forceinline__ void cons_body(const Shape& s, const CUtensorMap* tmq
                                           float* __restrict__ dg, const Gdn2& gd, const ConsPiece& pc,
                                           unsigned char* base, uint32_t tb) {
     const CUtensorMap &tmq = *tmq_, &tmk = *tmk_, &tmo = *tmo_, &tmg = *tmg_, &tmv = *tmv_;
-    const int Kw = NARROW ? s.K : D, Vw = NARROW ? s.V : D;   // row widths of the key- and value-side tensors
+    const int Kw = FX == 2 ? s.K : D, Vw = FX == 2 ? s.V : D;   // row widths of the key- and value-side tensors
+    const int Hg = FX ? s.Hg : s.H;                               // heads of the g, beta and erase rows
     float* sA = reinterpret_cast<float*>(base + C_A);
     const unsigned char* sK = base + C_K;
     const unsigned char* sQ = base + C_Q;
@@ -641,7 +646,7 @@ __device__ __forceinline__ void cons_body(const Shape& s, const CUtensorMap* tmq
         sMeta[2] = t0;
         if (u0 >= 0) {
             const int h0 = u0 % H;
-            cons_load_c<GATE>(sb, &tmk, &tmq, &tmg, h0, t0, bldC);
+            cons_load_c<GATE>(sb, &tmk, &tmq, &tmg, FX ? h0 / s.Gq : h0, FX ? h0 / s.Gg : h0, t0, bldC);
             if (pc.flags && !tc::wait_flag(pc.flags + u0, t.err)) atomicOr(t.err, 2);
             cons_load_x1(sb, f, bw, (size_t)u0, bldX1);
             cons_load_x2(sb, &tmo, &tmv, bw, (size_t)u0, h0, t0, bldX2);
@@ -672,13 +677,13 @@ __device__ __forceinline__ void cons_body(const Shape& s, const CUtensorMap* tmq
             }
         }
         const float beta_r =
-            (k == 0) ? ((tid < BT && tid < n && !GD2) ? bfx(beta + (size_t)(tok0 + tid) * H + h) : 0.f)
+            (k == 0) ? ((tid < BT && tid < n && !GD2) ? bfx(beta + (size_t)(tok0 + tid) * Hg + (FX ? h / s.Gg : h)) : 0.f)
                      : __bfloat162float(beta_nx);
         // the G tile for a scalar gate (or zeros): tile C_A is free since the previous unit's epilogue
         if (GATE != 2) {
             for (int idx = tid; idx < BT * D / 4; idx += CT) {
                 const int r = idx >> 5, c4 = (idx & 31) * 4;
-                const float x = (GATE == 1 && r < n) ? __ldg(g + (size_t)(tok0 + r) * H + h) : 0.f;
+                const float x = (GATE == 1 && r < n) ? __ldg(g + (size_t)(tok0 + r) * Hg + (FX ? h / s.Gg : h)) : 0.f;
                 *reinterpret_cast<float4*>(sA + r * D + c4) = make_float4(x, x, x, x);
             }
         }
@@ -794,13 +799,15 @@ __device__ __forceinline__ void cons_body(const Shape& s, const CUtensorMap* tmq
         // that unit starts; GatedDeltaNet-2: its erase and write rows (two 128-byte lines each)
         // into L2, so that its direct loads of them find them there
         if (nm[0] >= 0) {
-            const int nh = nm[0] % H;
+            const int nh = nm[0] % H, nhg = FX ? nh / s.Gg : nh;
             if (tid < BT)
-                beta_nx = (tid < nm[1] && !GD2) ? beta[(size_t)(nm[2] + tid) * H + nh] : __float2bfloat16_rn(0.f);
+                beta_nx = (tid < nm[1] && !GD2) ? beta[(size_t)(nm[2] + tid) * Hg + nhg] : __float2bfloat16_rn(0.f);
             if (GD2 && (tid >> 2) < nm[1]) {
-                const int w = (tid & 2) ? Vw : Kw;   // the row widths of the write and erase vectors
-                const bf16* vec = static_cast<const bf16*>((tid & 2) ? gd.write : gd.erase);
-                if ((tid & 1) * 64 < w) tc::prefetch_l2(vec + ((size_t)(nm[2] + (tid >> 2)) * H + nh) * w + (tid & 1) * 64);
+                const bool wr = (tid & 2) != 0;
+                const int w = wr ? Vw : Kw;   // the row widths of the write and erase vectors
+                const bf16* vec = static_cast<const bf16*>(wr ? gd.write : gd.erase);
+                const size_t row = (size_t)(nm[2] + (tid >> 2)) * (wr ? H : Hg) + (wr ? nh : nhg);
+                if ((tid & 1) * 64 < w) tc::prefetch_l2(vec + row * w + (tid & 1) * 64);
             }
         }
         // cumsum (4 segments of 16 rows per feature: thread = key kr, rows jb .. jb+15, the same
@@ -924,7 +931,7 @@ __device__ __forceinline__ void cons_body(const Shape& s, const CUtensorMap* tmq
                     const float av = (GATE == 2) ? al[q16] : 1.f;
                     const bool in = j < n;
                     const float eb = GD2 ? ((in && kr < Kw) ? bfx(static_cast<const bf16*>(gd.erase) +
-                                                                   ((size_t)(tok0 + j) * H + h) * Kw + kr) : 0.f)
+                                                                   ((size_t)(tok0 + j) * Hg + (FX ? h / s.Gg : h)) * Kw + kr) : 0.f)
                                          : bq[e];
                     ea[e] = in ? eb * kv * av : 0.f;
                     qa[e] = in ? scale * qv * av : 0.f;
@@ -1009,9 +1016,9 @@ __device__ __forceinline__ void cons_body(const Shape& s, const CUtensorMap* tmq
                                                   __fmul2_rn(__fmul2_rn(al2, nc22), make_float2(tps[e], tps[e + 1])));
                     float2 be2;
                     if (GD2) {
-                        const bf16* er = static_cast<const bf16*>(gd.erase) + ((size_t)(tok0 + j) * H + h) * Kw + kr;
+                        const bf16* er = static_cast<const bf16*>(gd.erase) + ((size_t)(tok0 + j) * Hg + (FX ? h / s.Gg : h)) * Kw + kr;
                         const bool kin = kr < Kw;   // erase rows of width K
-                        be2 = make_float2((kin && j < n) ? bfx(er) : 0.f, (kin && j + 1 < n) ? bfx(er + (size_t)H * Kw) : 0.f);
+                        be2 = make_float2((kin && j < n) ? bfx(er) : 0.f, (kin && j + 1 < n) ? bfx(er + (size_t)Hg * Kw) : 0.f);
                     } else {
                         be2 = make_float2(bv[e], bv[e + 1]);
                     }
@@ -1094,7 +1101,8 @@ __device__ __forceinline__ void cons_body(const Shape& s, const CUtensorMap* tmq
         tc::fence_before_sync();
         __syncthreads();
         if (tid == LDR && nm[0] >= 0) {
-            cons_load_c<GATE>(sb, &tmk, &tmq, &tmg, nm[0] % H, nm[2], bldC);
+            const int nh = nm[0] % H;
+            cons_load_c<GATE>(sb, &tmk, &tmq, &tmg, FX ? nh / s.Gq : nh, FX ? nh / s.Gg : nh, nm[2], bldC);
             ++nC;
         }
         if (!GD2 && tid < BT && tid < n)
@@ -1141,7 +1149,7 @@ __device__ __forceinline__ void cons_body(const Shape& s, const CUtensorMap* tmq
     }
 }
 
-template <int GATE, bool GD2, bool NARROW>
+template <int GATE, bool GD2, int FX>
 __global__ void __launch_bounds__(CT, 1)
     k_bwd_consumer_tc(Shape s, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmo, const __grid_constant__ CUtensorMap tmg,
@@ -1161,7 +1169,7 @@ __global__ void __launch_bounds__(CT, 1)
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tb = *tslot;
-    cons_body<GATE, GD2, NARROW>(s, &tmq, &tmk, &tmo, &tmg, &tmv, beta, g, t, f, bw, dq, dk, dv, dbeta, dg, gd, pc, base, tb);
+    cons_body<GATE, GD2, FX>(s, &tmq, &tmk, &tmo, &tmg, &tmv, beta, g, t, f, bw, dq, dk, dv, dbeta, dg, gd, pc, base, tb);
     tc::fence_before_sync();
     __syncthreads();
     if (threadIdx.x < 32) tc::tmem_dealloc(tb, 512);
@@ -1172,7 +1180,7 @@ __global__ void __launch_bounds__(CT, 1)
 // the other CTAs in the consumer loop, which takes the units latest chunk first and waits for each
 // unit's flag before loading its scan outputs. No CTA waits for one that is not running: the launch
 // is cooperative, so all of them are resident, and the scans never wait for the consumers.
-template <int GATE, bool GD2, bool NARROW>
+template <int GATE, bool GD2, int FX>
 __global__ void __launch_bounds__(CT, 1)
     k_bwd_joint_tc(Shape s, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmo, const __grid_constant__ CUtensorMap tmg,
@@ -1193,53 +1201,55 @@ __global__ void __launch_bounds__(CT, 1)
     tc::fence_after_sync();
     const uint32_t tb = *tslot;
     if ((int)blockIdx.x < s.N * s.H) {
-        bscan_body<NARROW>(s, &tmo, dht, t, f, bw, dh0, t.seq_order[(int)blockIdx.x / s.H], (int)blockIdx.x % s.H, 0, 0,
+        bscan_body<FX == 2>(s, &tmo, dht, t, f, bw, dh0, t.seq_order[(int)blockIdx.x / s.H], (int)blockIdx.x % s.H, 0, 0,
                    pc.flags, base, tb);
         tc::fence_async_smem();   // the scan's shared-memory writes before the consumer's tile loads land
         tc::fence_before_sync();
         __syncthreads();
         tc::fence_after_sync();
     }
-    cons_body<GATE, GD2, NARROW>(s, &tmq, &tmk, &tmo, &tmg, &tmv, beta, g, t, f, bw, dq, dk, dv, dbeta, dg, gd, pc, base, tb);
+    cons_body<GATE, GD2, FX>(s, &tmq, &tmk, &tmo, &tmg, &tmv, beta, g, t, f, bw, dq, dk, dv, dbeta, dg, gd, pc, base, tb);
     tc::fence_before_sync();
     __syncthreads();
     if (threadIdx.x < 32) tc::tmem_dealloc(tb, 512);
 }
 
-template <int GATE, bool GD2, bool NARROW>
+template <int GATE, bool GD2, int FX>
 cudaError_t run_consumer(const Shape& s, const void* q, const void* k, const void* v, const void* beta,
                          const float* g, const void* dout, Table t, FwdTC f, BwdTC b, void* dq, void* dk,
                          void* dv, void* dbeta, float* dg, cudaStream_t st, const Gdn2& gd, const ConsPiece& pc) {
-    cudaError_t e = set_smem_once<k_bwd_consumer_tc<GATE, GD2, NARROW>>(CONS_SMEM);
+    cudaError_t e = set_smem_once<k_bwd_consumer_tc<GATE, GD2, FX>>(CONS_SMEM);
     if (e != cudaSuccess) return e;
     CUtensorMap mq, mk, mo, mg, mv;
     memset(&mg, 0, sizeof(mg));
     // the inputs at their own widths K, V (<= D): the boxes' columns past them read as zeros
-    if (!tmap_rows_bf16(&mq, q, s.Ttot, s.H, s.K) || !tmap_rows_bf16(&mk, k, s.Ttot, s.H, s.K) ||
+    // (q, k with heads_q(s) heads, g with heads_g(s))
+    if (!tmap_rows_bf16(&mq, q, s.Ttot, heads_q(s), s.K) || !tmap_rows_bf16(&mk, k, s.Ttot, heads_q(s), s.K) ||
         !tmap_rows_bf16(&mo, dout, s.Ttot, s.H, s.V) || !tmap_rows_bf16(&mv, v, s.Ttot, s.H, s.V) ||
-        (GATE == 2 && !tmap_rows_f32(&mg, g, s.Ttot, s.H, s.K, D)))
+        (GATE == 2 && !tmap_rows_f32(&mg, g, s.Ttot, heads_g(s), s.K, D)))
         return cudaErrorInvalidValue;
     const long units = pc.L ? (long)s.N * pc.L * s.H : (long)s.NC * s.H;
     if (units <= 0) return cudaSuccess;
     if (units > 0x7fffffffL) return cudaErrorInvalidValue;
     const int grid = (int)(units < sm_count() ? units : sm_count());   // one CTA per SM, persistent
-    k_bwd_consumer_tc<GATE, GD2, NARROW><<<grid, CT, CONS_SMEM, st>>>(s, mq, mk, mo, mg, mv, (const bf16*)beta, g, t, f, b,
+    k_bwd_consumer_tc<GATE, GD2, FX><<<grid, CT, CONS_SMEM, st>>>(s, mq, mk, mo, mg, mv, (const bf16*)beta, g, t, f, b,
                                                          (bf16*)dq, (bf16*)dk, (bf16*)dv, (bf16*)dbeta, dg, gd, pc);
     return cudaGetLastError();
 }
 
-template <int GATE, bool GD2, bool NARROW>
+template <int GATE, bool GD2, int FX>
 cudaError_t run_joint(const Shape& s, const void* q, const void* k, const void* v, const void* beta, const float* g,
                       const void* dout, const float* dht, float* dh0, Table t, FwdTC f, BwdTC b, void* dq, void* dk,
                       void* dv, void* dbeta, float* dg, cudaStream_t st, const Gdn2& gd, const ConsPiece& pc) {
-    cudaError_t e = set_smem_once<k_bwd_joint_tc<GATE, GD2, NARROW>>(JOINT_SMEM);
+    cudaError_t e = set_smem_once<k_bwd_joint_tc<GATE, GD2, FX>>(JOINT_SMEM);
     if (e != cudaSuccess) return e;
     CUtensorMap mq, mk, mo, mg, mv;
     memset(&mg, 0, sizeof(mg));
     // the inputs at their own widths K, V (<= D): the boxes' columns past them read as zeros
-    if (!tmap_rows_bf16(&mq, q, s.Ttot, s.H, s.K) || !tmap_rows_bf16(&mk, k, s.Ttot, s.H, s.K) ||
+    // (q, k with heads_q(s) heads, g with heads_g(s))
+    if (!tmap_rows_bf16(&mq, q, s.Ttot, heads_q(s), s.K) || !tmap_rows_bf16(&mk, k, s.Ttot, heads_q(s), s.K) ||
         !tmap_rows_bf16(&mo, dout, s.Ttot, s.H, s.V) || !tmap_rows_bf16(&mv, v, s.Ttot, s.H, s.V) ||
-        (GATE == 2 && !tmap_rows_f32(&mg, g, s.Ttot, s.H, s.K, D)))
+        (GATE == 2 && !tmap_rows_f32(&mg, g, s.Ttot, heads_g(s), s.K, D)))
         return cudaErrorInvalidValue;
     const int grid = sm_count();
     if (s.N * s.H > grid || !pc.flags || !pc.ctr) return cudaErrorInvalidValue;
@@ -1253,7 +1263,7 @@ cudaError_t run_joint(const Shape& s, const void* q, const void* k, const void* 
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_bwd_joint_tc<GATE, GD2, NARROW>, s, mq, mk, mo, mg, mv, dht, dh0, (const bf16*)beta, g,
+    return cudaLaunchKernelEx(&cfg, k_bwd_joint_tc<GATE, GD2, FX>, s, mq, mk, mo, mg, mv, dht, dh0, (const bf16*)beta, g,
                               t, f, b, (bf16*)dq, (bf16*)dk, (bf16*)dv, (bf16*)dbeta, dg, gd, pc);
 }
 
@@ -1263,16 +1273,17 @@ cudaError_t launch_bwd_joint_tc(const Shape& s, int gate, const void* q, const v
                                 const void* beta, const float* g, const void* dout, const float* dht, float* dh0,
                                 Table t, FwdTC f, BwdTC b, void* dq, void* dk, void* dv, void* dbeta, float* dg,
                                 cudaStream_t st, const Gdn2& gd, const ConsPiece& pc) {
-    const bool narrow = s.K != D || s.V != D;   // inputs narrower than the tiles
-#define KDA_JOINT(G, X)                                                                                          \
-    (narrow ? run_joint<G, X, true>(s, q, k, v, beta, g, dout, dht, dh0, t, f, b, dq, dk, dv, dbeta, dg, st, gd, pc) \
-            : run_joint<G, X, false>(s, q, k, v, beta, g, dout, dht, dh0, t, f, b, dq, dk, dv, dbeta, dg, st, gd, pc))
+    // narrower inputs (and grouped heads with them), grouped heads at the tile width, or neither
+    const int fx = (s.K != D || s.V != D) ? 2 : (s.Gq != 1 || s.Gg != 1) ? 1 : 0;
+#define KDA_JOINT_FX(G, X, F) run_joint<G, X, F>(s, q, k, v, beta, g, dout, dht, dh0, t, f, b, dq, dk, dv, dbeta, dg, st, gd, pc)
+#define KDA_JOINT(G, X) (fx == 2 ? KDA_JOINT_FX(G, X, 2) : fx == 1 ? KDA_JOINT_FX(G, X, 1) : KDA_JOINT_FX(G, X, 0))
     switch (gate) {
         case 0: return gd.erase ? KDA_JOINT(0, true) : KDA_JOINT(0, false);
         case 1: return gd.erase ? KDA_JOINT(1, true) : KDA_JOINT(1, false);
         default: return gd.erase ? KDA_JOINT(2, true) : KDA_JOINT(2, false);
     }
 #undef KDA_JOINT
+#undef KDA_JOINT_FX
 }
 
 cudaError_t launch_bwd_scan_tc(const Shape& s, const void* dout, const float* dht, Table t, FwdTC f, BwdTC b,
@@ -1290,10 +1301,12 @@ cudaError_t launch_bwd_consumer_tc(const Shape& s, int gate, const void* q, cons
                                    const void* beta, const float* g, const void* dout, Table t, FwdTC f,
                                    BwdTC b, void* dq, void* dk, void* dv, void* dbeta, float* dg,
                                    cudaStream_t st, const Gdn2& gd, const ConsPiece& pc) {
-    const bool narrow = s.K != D || s.V != D;   // inputs narrower than the tiles
-#define KDA_CONS(G, X)                                                                                         \
-    (narrow ? run_consumer<G, X, true>(s, q, k, v, beta, g, dout, t, f, b, dq, dk, dv, dbeta, dg, st, gd, pc) \
-            : run_consumer<G, X, false>(s, q, k, v, beta, g, dout, t, f, b, dq, dk, dv, dbeta, dg, st, gd, pc))
+    // narrower inputs or grouped heads (the consumer's flexible variant keeps its registers at the
+    // tile width too), or neither
+    const bool flex = s.K != D || s.V != D || s.Gq != 1 || s.Gg != 1;
+#define KDA_CONS(G, X)                                                                                    \
+    (flex ? run_consumer<G, X, 2>(s, q, k, v, beta, g, dout, t, f, b, dq, dk, dv, dbeta, dg, st, gd, pc) \
+          : run_consumer<G, X, 0>(s, q, k, v, beta, g, dout, t, f, b, dq, dk, dv, dbeta, dg, st, gd, pc))
     switch (gate) {
         case 0: return gd.erase ? KDA_CONS(0, true) : KDA_CONS(0, false);
         case 1: return gd.erase ? KDA_CONS(1, true) : KDA_CONS(1, false);

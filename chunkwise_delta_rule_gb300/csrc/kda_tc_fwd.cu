@@ -193,6 +193,7 @@ __global__ void __launch_bounds__(PT, 2)
     if (n <= 0) return;
     const int tok0 = t.chunk_tok0[c];
     const int H = s.H;
+    const int hq = h / s.Gq, hg = h / s.Gg, Hg = heads_g(s);   // heads of q, k and of g, beta, erase
     const size_t ch = (size_t)c * H + h;
     const float scale = s.scale;
     const int c8 = (tid & 15) * 8;   // the 8 feature columns of this thread in every row pass
@@ -205,27 +206,29 @@ __global__ void __launch_bounds__(PT, 2)
         tc::mbar_init(bld, 1);
         tc::fence_mbar_init();
         tc::mbar_arrive_expect_tx(bld, 6 * 8192 + (GATE == 2 ? BT * D * 4 : 0));
-        tc::tma_load3(sb + P_B1, &tmk, 0, h, tok0, bld);
-        tc::tma_load3(sb + P_B1 + 8192, &tmk, 64, h, tok0, bld);
-        tc::tma_load3(sb + P_A1 + 8192, &tmq, 0, h, tok0, bld);
-        tc::tma_load3(sb + P_A1 + 24576, &tmq, 64, h, tok0, bld);
+        tc::tma_load3(sb + P_B1, &tmk, 0, hq, tok0, bld);
+        tc::tma_load3(sb + P_B1 + 8192, &tmk, 64, hq, tok0, bld);
+        tc::tma_load3(sb + P_A1 + 8192, &tmq, 0, hq, tok0, bld);
+        tc::tma_load3(sb + P_A1 + 24576, &tmq, 64, hq, tok0, bld);
         tc::tma_load3(sb + P_V, &tmv, 0, h, tok0, bld);
         tc::tma_load3(sb + P_V + 8192, &tmv, 64, h, tok0, bld);
-        if (GATE == 2) tc::tma_load3(sb + P_ALPHA, &tmg, 0, h, tok0, bld);
+        if (GATE == 2) tc::tma_load3(sb + P_ALPHA, &tmg, 0, hg, tok0, bld);
     }
-    const float beta_r = (tid < BT && tid < n && !GD2) ? bfx(beta + (size_t)(tok0 + tid) * H + h) : 0.f;
+    const float beta_r = (tid < BT && tid < n && !GD2) ? bfx(beta + (size_t)(tok0 + tid) * Hg + hg) : 0.f;
     // GatedDeltaNet-2: this chunk's erase and write rows (two 128-byte lines each) into L2 while
     // the cumsum runs; the operand pass reads them
     if (GD2 && (tid >> 2) < n) {
-        const int w = (tid & 2) ? s.V : s.K;   // the row widths of the write and erase vectors
-        const bf16* vec = static_cast<const bf16*>((tid & 2) ? gd.write : gd.erase);
-        if ((tid & 1) * 64 < w) tc::prefetch_l2(vec + ((size_t)(tok0 + (tid >> 2)) * H + h) * w + (tid & 1) * 64);
+        const bool wr = (tid & 2) != 0;
+        const int w = wr ? s.V : s.K;   // the row widths of the write and erase vectors
+        const bf16* vec = static_cast<const bf16*>(wr ? gd.write : gd.erase);
+        const size_t row = (size_t)(tok0 + (tid >> 2)) * (wr ? H : Hg) + (wr ? h : hg);
+        if ((tid & 1) * 64 < w) tc::prefetch_l2(vec + row * w + (tid & 1) * 64);
     }
     if (GATE != 2) {
         // scalar gate: the G tile repeats the token's log-decay; no gate: zeros
         for (int idx = tid; idx < BT * D / 4; idx += PT) {
             const int r = idx >> 5, c4 = (idx & 31) * 4;
-            const float x = (GATE == 1 && r < n) ? __ldg(g + (size_t)(tok0 + r) * H + h) : 0.f;
+            const float x = (GATE == 1 && r < n) ? __ldg(g + (size_t)(tok0 + r) * Hg + hg) : 0.f;
             *reinterpret_cast<float4*>(sA + r * LG + c4) = make_float4(x, x, x, x);
         }
     }
@@ -312,8 +315,9 @@ __global__ void __launch_bounds__(PT, 2)
                 const int i = (tid + PT * u) >> 4;
                 er_all[u] = wr_all[u] = make_uint4(0, 0, 0, 0);
                 if (i < n) {
-                    const size_t row = (size_t)(tok0 + i) * H + h;   // widths K and V, zero past them
-                    if (c8 < s.K) er_all[u] = *reinterpret_cast<const uint4*>(static_cast<const bf16*>(gd.erase) + row * s.K + c8);
+                    const size_t row = (size_t)(tok0 + i) * H + h, rowe = (size_t)(tok0 + i) * Hg + hg;
+                    // widths K and V, zero past them
+                    if (c8 < s.K) er_all[u] = *reinterpret_cast<const uint4*>(static_cast<const bf16*>(gd.erase) + rowe * s.K + c8);
                     if (c8 < s.V) wr_all[u] = *reinterpret_cast<const uint4*>(static_cast<const bf16*>(gd.write) + row * s.V + c8);
                 }
             }
@@ -953,8 +957,10 @@ cudaError_t run_prep(const Shape& s, const void* q, const void* k, const void* v
     CUtensorMap mq, mk, mv, mg;
     memset(&mg, 0, sizeof(mg));
     // the inputs at their own widths K, V (<= D): the boxes' columns past them read as zeros
-    if (!tmap_rows_bf16(&mq, q, s.Ttot, s.H, s.K) || !tmap_rows_bf16(&mk, k, s.Ttot, s.H, s.K) ||
-        !tmap_rows_bf16(&mv, v, s.Ttot, s.H, s.V) || (GATE == 2 && !tmap_rows_f32(&mg, g, s.Ttot, s.H, s.K, D)))
+    // (q, k with heads_q(s) heads, g with heads_g(s))
+    if (!tmap_rows_bf16(&mq, q, s.Ttot, heads_q(s), s.K) || !tmap_rows_bf16(&mk, k, s.Ttot, heads_q(s), s.K) ||
+        !tmap_rows_bf16(&mv, v, s.Ttot, s.H, s.V) ||
+        (GATE == 2 && !tmap_rows_f32(&mg, g, s.Ttot, heads_g(s), s.K, D)))
         return cudaErrorInvalidValue;
     dim3 grid(s.NC, s.H);
     k_prep_tc<GATE, BWD, GD2><<<grid, PT, PREP_SMEM, st>>>(s, mq, mk, mv, mg, (const bf16*)beta, g, t, f, gd);

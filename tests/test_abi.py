@@ -190,9 +190,19 @@ def test_grouped_value_heads_are_validated_and_sized():
     g = _prob(H=2)
     g.HV = 6
     flat = _prob(H=6)   # the same problem with one key head per value head
-    copy = up(2 * 2 * 130 * 6 * 128)   # bf16 q (or k) copied per value head
-    assert _ws(g, 0) == _ws(flat, 0) + 2 * copy
-    assert _ws(g, 1) == _ws(flat, 1) + 4 * copy
+    copy = up(2 * 2 * 130 * 6 * 128)   # bf16 q (or k, dq, dk) per value head
+    # tensor-core path: q, k read in place by key head; the backward's dq, dk per value head
+    assert _ws(g, 0) == _ws(flat, 0)
+    assert _ws(g, 1) == _ws(flat, 1) + 2 * copy
+    # with the prologue (q, k normalised first) or fp32 I/O, q and k are copied per value head
+    for kw, es in ((dict(), 2), (dict(io=1), 4)):
+        gp, fp = _prob(H=2, **kw), _prob(H=6, **kw)
+        gp.HV = 6
+        if not kw:
+            gp.qk_l2norm = fp.qk_l2norm = 1
+        one = up(es * 2 * 130 * 6 * 128)
+        assert _ws(gp, 0) == _ws(fp, 0) + 2 * one
+        assert _ws(gp, 1) == _ws(fp, 1) + 4 * one
 
 
 def test_unequal_widths_pad_to_the_working_width():
@@ -253,12 +263,18 @@ def test_wide_values_run_as_value_blocks():
     inner = _prob(V=128)
     inner.HV = 6
     T, Hv, K, NB = 2 * 130, 3, 128, 2
-    # beta and g repeated per block, the blocks' final states
-    split_f = up(2 * T * Hv * NB) + up(4 * T * Hv * NB * K) + up(4 * 2 * Hv * K * 256)
+    # tensor-core blocks at their own width read beta and g in place (block value head j reads
+    # head j / NB): the blocks' final states only
+    split_f = up(4 * 2 * Hv * K * 256)
     assert _ws(p, 0) == _ws(inner, 0) + split_f
     # backward adds the blocks' dbeta, dg, dht and dh0
     split_b = split_f + up(2 * T * Hv * NB) + up(4 * T * Hv * NB * K) + 2 * up(4 * 2 * Hv * K * 256)
     assert _ws(p, 1) == _ws(inner, 1) + split_b
+    # with the prologue, beta and g repeat per block
+    pp, ip = _prob(V=256), _set(_prob(V=128), HV=6)
+    pp.qk_l2norm = ip.qk_l2norm = 1
+    split_f = up(2 * T * Hv * NB) + up(4 * T * Hv * NB * K) + up(4 * 2 * Hv * K * 256)
+    assert _ws(pp, 0) == _ws(ip, 0) + split_f
     assert lib.kda_saved_size(ctypes.byref(_prob(V=256, save=1))) == \
         lib.kda_saved_size(ctypes.byref(_set(_prob(V=128, save=1), HV=6)))
     # V = 201: two blocks of 101, value rows padded to 202 (v and o in the forward)

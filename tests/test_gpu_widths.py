@@ -227,3 +227,47 @@ def test_native_widths_backward_schedules_agree_bitwise():
                                      seq_starts=case.seq_starts, h0=p["h0"], do=p["do"], dht=p["dht"],
                                      qk_norm=False, erase=None, write=None)
     compare(case, got, ref, 1, TOL["bf16"])
+
+
+# Grouped heads and value blocks on the tensor-core path without the prologue read q, k (value
+# head j: key head j / G, times the block count) and g, beta, erase (head j / NB for value
+# blocks) in place; the cases meet every input the divisors touch: both gate kinds, the
+# GatedDeltaNet-2 erase rows, widths below 128 and value blocks together with grouped heads.
+@pytest.mark.parametrize("gate,K,V,G,gdn2", [("channel", 128, 256, 2, False), ("channel", 128, 256, 1, True),
+                                              ("scalar", 128, 384, 2, False), ("channel", 80, 112, 2, True),
+                                              ("none", 96, 160, 2, False)])
+def test_grouped_inputs_read_in_place(gate, K, V, G, gdn2):
+    case = width_case("bf16", gate, 2, 100, 4, K, V, 116)
+    got, ref = run_both(case, G=G, gdn2=gdn2)
+    compare(case, got, ref, G, TOL["bf16"])
+
+
+def test_grouped_inputs_read_in_place_strong_decay():
+    """Chunks whose gate range exceeds the tensor-core prep's limit go to the CUDA-core kernels,
+    which read q, k, g and erase through the same head divisors."""
+    case = make_case(io="bf16", gate="channel", B=1, T=200, H=4, K=128, V=256, seed=117, g_shift=-4.0, g_min=-8.0)
+    G = torch.cumsum(case.g.double(), dim=1) / np.log(2.0)
+    assert float((G[:, :64].max(dim=1).values - G[:, :64].min(dim=1).values).max()) > 80
+    got, ref = run_both(case, G=2, gdn2=True)
+    compare(case, got, ref, 2, TOL["bf16"])
+
+
+def test_grouped_heads_in_place_equal_expanded_inputs():
+    """Value head j reading key head j / 2 in place gives, bit for bit, what the caller gets by
+    repeating q and k per value head (dq, dk as the sums over each pair, rounded once)."""
+    import chunkwise_delta_rule_gb300 as kda
+    case = width_case("bf16", "channel", 2, 150, 4, 128, 128, 118)
+    c = case.to("cuda")
+    qk = c.q[:, :, ::2].contiguous(), c.k[:, :, ::2].contiguous()
+    runs = []
+    for q, k in (qk, (qk[0].repeat_interleave(2, 2), qk[1].repeat_interleave(2, 2))):
+        p = kda.make_problem(q, k, c.v, c.g, c.beta, gate="channel", scale=case.scale, initial_state=c.h0,
+                             save_policy=1)
+        o, ht, sv = kda.kda_chunk_fwd(p)
+        runs.append((o, ht) + tuple(kda.kda_chunk_bwd(p, c.do, c.dht, saved=sv)))
+    torch.cuda.synchronize()
+    for name, a, b in zip(("o", "ht", "dq", "dk", "dv", "dg", "dbeta", "dh0"), *runs):
+        if name in ("dq", "dk"):
+            x = b.float().reshape(b.shape[0], b.shape[1], b.shape[2] // 2, 2, b.shape[3])
+            b = (x[..., 0, :] + x[..., 1, :]).to(b.dtype)
+        assert torch.equal(a, b), name
