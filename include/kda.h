@@ -39,10 +39,11 @@
  *    number of packed sequences.
  *  - Arguments are validated before anything is enqueued; on any error
  *    nothing is written and kda_last_error() describes the problem.
- *  - Widths: the chunked calls take any K <= 256 and V <= 4096 (K = V = 128
- *    or 256 natively, and 64 with fp32 I/O; other widths zero-padded, V above
- *    128 as value blocks, above 256 when K > 128; see kda_problem); the
- *    token-by-token call takes K = 64, 128, 160, 192 and 256.
+ *  - Widths: the chunked calls take any K <= 256 and V <= 4096 (bf16 K, V
+ *    multiples of 8 up to 128 and K = V = 256 natively, fp32 K = V = 64 or
+ *    128; other widths zero-padded, V above 128 as value blocks, above 256
+ *    when K > 128; see kda_problem); the token-by-token call takes K = 64,
+ *    128, 160, 192 and 256.
  */
 #ifndef KDA_H_
 #define KDA_H_
@@ -77,10 +78,13 @@ typedef enum { KDA_GATE_NONE = 0, KDA_GATE_SCALAR = 1, KDA_GATE_CHANNEL = 2 } kd
 typedef struct {
     int B, T, H, K, V;          /* batch, tokens per sequence (total tokens when packed),
                                    heads, key width (1..256), value width (1..4096).
-                                   Other than K = V = 128 or 256 (or 64 with fp32 I/O)
-                                   the chunked calls run zero-padded: bf16 I/O with
-                                   K <= 128 to 128, fp32 I/O to 64 (K, V <= 64) or 128,
-                                   K > 128 to 256 (the value side too). V above M runs as
+                                   bf16 I/O with K, V <= 128 both multiples of 8 runs
+                                   at its own widths (with the in-operator prologue:
+                                   K = 64 or 128); K = V = 256, and K = V = 64 or 128
+                                   with fp32 I/O, run as they are. Other widths run
+                                   zero-padded: bf16 I/O with K <= 128 to 128, fp32 I/O
+                                   to 64 (K, V <= 64) or 128, K > 128 to 256 (the value
+                                   side too). V above M runs as
                                    ceil(V / M) value blocks, M = 128 (K <= 128) or 256,
                                    each a value head of its own (the delta-rule update
                                    moves every value column of the state independently,
