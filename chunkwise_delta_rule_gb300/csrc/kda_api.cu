@@ -23,6 +23,7 @@ struct Dims {
     int N = 0, NC = 0, Ttot = 0, H = 0;
     int D = 0, V = 0;   // key and value widths of the problem
     int WD = 0;         // working width of the chunk intermediates (the tile width of the path)
+    bool alk = false;   // per-channel gate: the tensor-core prep saves alpha for the backward consumer
     int per = 0;        // chunks per sequence of an equal-length batch (0: packed sequences)
 };
 
@@ -66,6 +67,7 @@ kda_status check_dims(const kda_problem* p, Dims& d) {
     // CUDA-core path's problems are padded to K = V = 64, 128 or 256 before they get here)
     d.WD = (p->io == KDA_BF16 && p->K <= 128 && p->V <= 128) ? 128 : p->K;
     d.H = p->H;
+    d.alk = p->gate == KDA_GATE_CHANNEL;
     const long long per = (p->T + kda::BT - 1) / kda::BT;
     if (p->cu_seqlens) {
         if (p->B != 1) return fail(KDA_ERR_INVALID_ARG, "packed sequences need B == 1");
@@ -105,7 +107,8 @@ Layout layout(const Dims& d) {
     L.bwd = up(4 * chd * BT * D) * 4 + up(4 * chd * D * D) + up(4 * chd * BT * BT) * 2 +
             up(4 * chd * D) + up(4 * chd * BT);
     L.ftc = up(2 * chd * BT * D) * 4 + up(2 * chd * BT * BT) + up(4 * chd * D) + up(4 * chd) + up(4 * (chd + 1));
-    L.ftc_b = up(2 * chd * BT * BT) + up(2 * chd * D * D) + up(2 * chd * BT * D);
+    L.ftc_b = up(2 * chd * BT * BT) + up(2 * chd * D * D) + up(2 * chd * BT * D) +
+              (d.alk ? up(4 * chd * kda::ALK_UNIT) : 0);
     L.btc = up(2 * chd * D * D) + up(2 * chd * BT * D);
     L.wscr = up(4 * chd * BT * D) * 3 + up(4 * chd * BT * BT) * 2 + up(4 * chd * D) + up(4 * chd * BT);
     if (d.per) L.piece = 2 * up(4 * N * H * (size_t)d.D * d.V) + up(4 * kda::MAX_PIECES) + up(4 * chd);
@@ -180,6 +183,7 @@ void carve_fwd_tc(Carver& c, const Dims& d, kda::FwdTC& f, bool bwd_arrays) {
         f.AI = c.take<__nv_bfloat16>(2 * chd * BT * BT);
         f.HS = c.take<__nv_bfloat16>(2 * chd * D * D);
         f.R = c.take<__nv_bfloat16>(2 * chd * BT * D);
+        if (d.alk) f.ALK = c.take<float>(4 * chd * kda::ALK_UNIT);
     }
 }
 

@@ -92,9 +92,15 @@ struct FwdTC {
     int32_t* WLIST;       // [1 + NC*H]   count, then chunk slot * H + head of every WIDE chunk
     // backward-only (null in the forward)
     __nv_bfloat16* AI;    // [NC,H,BT,BT] A = (I + L)^-1
+    float* ALK;           // [NC,H][ALK_UNIT] per-channel gate: alpha = 2^(G2 - c) as the backward
+                          // consumer holds it (key-major rows of BT tokens, 16-byte groups swizzled
+                          // by key), then 2^c and 2^(G2_last - c) per key
     __nv_bfloat16* HS;    // [NC,H,D,D]   state entering the chunk, [key][value]
     __nv_bfloat16* R;     // [NC,H,BT,D]  corrections
 };
+
+// Floats per (chunk, head) of FwdTC::ALK: the [128][BT] alpha image and two rows of 128.
+constexpr int ALK_UNIT = 128 * BT + 2 * 128;
 
 // Backward intermediates of the tensor-core path (bf16, [row][col] as named).
 struct BwdTC {

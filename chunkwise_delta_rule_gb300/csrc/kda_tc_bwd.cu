@@ -527,17 +527,21 @@ __device__ __forceinline__ int cons_find(int& i, int units, const ConsPiece& pc,
     return -1;
 }
 
-// Load group C from tok0: k, q of head hq by TMA in SW128 rows, g (per-channel gate) of head hg as
-// fp32 rows.
+// Load group C of unit ch from tok0: k, q of head hq by TMA in SW128 rows; per-channel gate: the
+// prep's alpha (fp32 token rows) and its 2^c, 2^(G2_last - c) rows as they are.
 template <int GATE>
 __device__ __forceinline__ void cons_load_c(uint32_t sb, const CUtensorMap* tmk, const CUtensorMap* tmq,
-                                            const CUtensorMap* tmg, int hq, int hg, int tok0, uint64_t* b) {
-    tc::mbar_arrive_expect_tx(b, 2 * BT * D * 2 + (GATE == 2 ? BT * D * 4 : 0));
+                                            const FwdTC& f, size_t ch, int hq, int tok0, uint64_t* b) {
+    tc::mbar_arrive_expect_tx(b, 2 * BT * D * 2 + (GATE == 2 ? 4 * ALK_UNIT : 0));
     tc::tma_load3(sb + C_K, tmk, 0, hq, tok0, b);
     tc::tma_load3(sb + C_K + 8192, tmk, 64, hq, tok0, b);
     tc::tma_load3(sb + C_Q, tmq, 0, hq, tok0, b);
     tc::tma_load3(sb + C_Q + 8192, tmq, 64, hq, tok0, b);
-    if (GATE == 2) tc::tma_load3(sb + C_A, tmg, 0, hg, tok0, b);
+    if (GATE == 2) {
+        const float* img = f.ALK + ch * ALK_UNIT;
+        tc::bulk_g2s(sb + C_A, img, 4 * BT * D, b);
+        tc::bulk_g2s(sb + C_MISC + 4 * M_C2, img + BT * D, 4 * 2 * D, b);
+    }
 }
 
 // Load group X1 of unit ch: R in rows 0..63 and S in rows 64..191 of each atom column of the
@@ -588,13 +592,13 @@ __device__ __forceinline__ bool cons_wait(uint64_t* b, int& w, int32_t* err) {
 // of 8, at most D).
 template <int GATE, bool GD2, int FX>
 __device__ __forceinline__ void cons_body(const Shape& s, const CUtensorMap* tmq_, const CUtensorMap* tmk_,
-                                          const CUtensorMap* tmo_, const CUtensorMap* tmg_, const CUtensorMap* tmv_,
+                                          const CUtensorMap* tmo_, const CUtensorMap* tmv_,
                                           const bf16* __restrict__ beta, const float* __restrict__ g, const Table& t,
                                           const FwdTC& f, const BwdTC& bw, bf16* __restrict__ dq,
                                           bf16* __restrict__ dk, bf16* __restrict__ dv, bf16* __restrict__ dbeta,
                                           float* __restrict__ dg, const Gdn2& gd, const ConsPiece& pc,
                                           unsigned char* base, uint32_t tb) {
-    const CUtensorMap &tmq = *tmq_, &tmk = *tmk_, &tmo = *tmo_, &tmg = *tmg_, &tmv = *tmv_;
+    const CUtensorMap &tmq = *tmq_, &tmk = *tmk_, &tmo = *tmo_, &tmv = *tmv_;
     const int Kw = FX == 2 ? s.K : D, Vw = FX == 2 ? s.V : D;   // row widths of the key- and value-side tensors
     const int Hg = FX ? s.Hg : s.H;                               // heads of the g, beta and erase rows
     float* sA = reinterpret_cast<float*>(base + C_A);
@@ -646,7 +650,7 @@ __device__ __forceinline__ void cons_body(const Shape& s, const CUtensorMap* tmq
         sMeta[2] = t0;
         if (u0 >= 0) {
             const int h0 = u0 % H;
-            cons_load_c<GATE>(sb, &tmk, &tmq, &tmg, FX ? h0 / s.Gq : h0, FX ? h0 / s.Gg : h0, t0, bldC);
+            cons_load_c<GATE>(sb, &tmk, &tmq, f, (size_t)u0, FX ? h0 / s.Gq : h0, t0, bldC);
             if (pc.flags && !tc::wait_flag(pc.flags + u0, t.err)) atomicOr(t.err, 2);
             cons_load_x1(sb, f, bw, (size_t)u0, bldX1);
             cons_load_x2(sb, &tmo, &tmv, bw, (size_t)u0, h0, t0, bldX2);
@@ -810,23 +814,12 @@ __device__ __forceinline__ void cons_body(const Shape& s, const CUtensorMap* tmq
                 if ((tid & 1) * 64 < w) tc::prefetch_l2(vec + row * w + (tid & 1) * 64);
             }
         }
-        // cumsum (4 segments of 16 rows per feature: thread = key kr, rows jb .. jb+15, the same
-        // key and tokens this thread handles in every later pass), anchors, alpha; segments meet
-        // in shared memory. alpha, k and q are then rewritten key-major over their own tiles.
+        // alpha of this thread's key kr and rows jb .. jb+15 (the same key and tokens it handles in
+        // every later pass). Per-channel gate: the prep's, as token rows. Otherwise the cumsum (4
+        // segments of 16 rows per feature, meeting in shared memory), the midpoint anchor and
+        // alpha = 2^(G2 - c). alpha, k and q are then rewritten key-major over their own tiles.
         {
             float* xt = reinterpret_cast<float*>(base + X_SCR);   // [3][4][128] totals, maxima, minima
-            float x[16];
-            float acc = 0.f, hi = -INFINITY, lo = INFINITY;
-#pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                const int row = jb + r;
-                acc += (row < n) ? sA[row * D + kr] : 0.f;
-                x[r] = acc * LOG2E;
-                if (row < n) {
-                    hi = fmaxf(hi, x[r]);
-                    lo = fminf(lo, x[r]);
-                }
-            }
             uint32_t kk[8], qq[8];   // k and q of this key for the 16 rows, bf16 pairs
 #pragma unroll
             for (int r = 0; r < 16; r += 2) {
@@ -836,35 +829,56 @@ __device__ __forceinline__ void cons_body(const Shape& s, const CUtensorMap* tmq
                 qq[r / 2] = (uint32_t)*reinterpret_cast<const uint16_t*>(sQ + o0) |
                             ((uint32_t)*reinterpret_cast<const uint16_t*>(sQ + o1) << 16);
             }
-            xt[grp * D + kr] = acc * LOG2E;
-            xt[4 * D + grp * D + kr] = hi;
-            xt[8 * D + grp * D + kr] = lo;
-            __syncthreads();   // (also: every g, k, q read before the key-major tiles overwrite them)
-            float off = 0.f, run = 0.f, hh = -INFINITY, ll = INFINITY;
+            float x[16];
+            float acc = 0.f, hi = -INFINITY, lo = INFINITY;
 #pragma unroll
-            for (int s2 = 0; s2 < 4; ++s2) {
-                const float ts = xt[s2 * D + kr];
-                if (s2 < grp) off = run + ts;
-                hh = fmaxf(hh, xt[4 * D + s2 * D + kr] + run);
-                ll = fminf(ll, xt[8 * D + s2 * D + kr] + run);
-                run += ts;
+            for (int r = 0; r < 16; ++r) {
+                const int row = jb + r;
+                if (GATE == 2) {
+                    x[r] = sA[row * D + kr];
+                } else {
+                    acc += (row < n) ? sA[row * D + kr] : 0.f;
+                    x[r] = acc * LOG2E;
+                    if (row < n) {
+                        hi = fmaxf(hi, x[r]);
+                        lo = fminf(lo, x[r]);
+                    }
+                }
             }
-            const float cc = (GATE == 0) ? 0.f : 0.5f * (hh + ll);
+            if (GATE != 2) {
+                xt[grp * D + kr] = acc * LOG2E;
+                xt[4 * D + grp * D + kr] = hi;
+                xt[8 * D + grp * D + kr] = lo;
+            }
+            __syncthreads();   // (also: every alpha (or g), k, q read before the key-major tiles overwrite them)
+            if (GATE != 2) {
+                float off = 0.f, run = 0.f, hh = -INFINITY, ll = INFINITY;
+#pragma unroll
+                for (int s2 = 0; s2 < 4; ++s2) {
+                    const float ts = xt[s2 * D + kr];
+                    if (s2 < grp) off = run + ts;
+                    hh = fmaxf(hh, xt[4 * D + s2 * D + kr] + run);
+                    ll = fminf(ll, xt[8 * D + s2 * D + kr] + run);
+                    run += ts;
+                }
+                const float cc = (GATE == 0) ? 0.f : 0.5f * (hh + ll);
+#pragma unroll
+                for (int r = 0; r < 16; ++r) x[r] = exp2f(x[r] + off - cc);
+                if (grp == 0) {
+                    sC2[kr] = exp2f(cc);
+                    sAL[kr] = exp2f(run - cc);   // run: G2 at the chunk end
+                }
+            }
 #pragma unroll
             for (int m = 0; m < 4; ++m)
                 *reinterpret_cast<float4*>(sA + akm4(kr, 4 * grp + m)) =
-                    make_float4(exp2f(x[4 * m] + off - cc), exp2f(x[4 * m + 1] + off - cc),
-                                exp2f(x[4 * m + 2] + off - cc), exp2f(x[4 * m + 3] + off - cc));
+                    make_float4(x[4 * m], x[4 * m + 1], x[4 * m + 2], x[4 * m + 3]);
 #pragma unroll
             for (int b2 = 0; b2 < 2; ++b2) {
                 *reinterpret_cast<uint4*>(sKm + kkm8(kr, 2 * grp + b2)) =
                     make_uint4(kk[4 * b2], kk[4 * b2 + 1], kk[4 * b2 + 2], kk[4 * b2 + 3]);
                 *reinterpret_cast<uint4*>(sQm + kkm8(kr, 2 * grp + b2)) =
                     make_uint4(qq[4 * b2], qq[4 * b2 + 1], qq[4 * b2 + 2], qq[4 * b2 + 3]);
-            }
-            if (grp == 0) {
-                sC2[kr] = exp2f(cc);
-                sAL[kr] = exp2f(run - cc);   // run: G2 at the chunk end
             }
         }
         // (K zeta)^T into TMEM (the A operand of [T_e ; T_q]^T; this thread's key and 16 tokens,
@@ -1102,7 +1116,7 @@ __device__ __forceinline__ void cons_body(const Shape& s, const CUtensorMap* tmq
         __syncthreads();
         if (tid == LDR && nm[0] >= 0) {
             const int nh = nm[0] % H;
-            cons_load_c<GATE>(sb, &tmk, &tmq, &tmg, FX ? nh / s.Gq : nh, FX ? nh / s.Gg : nh, nm[2], bldC);
+            cons_load_c<GATE>(sb, &tmk, &tmq, f, (size_t)nm[0], FX ? nh / s.Gq : nh, nm[2], bldC);
             ++nC;
         }
         if (!GD2 && tid < BT && tid < n)
@@ -1152,8 +1166,8 @@ __device__ __forceinline__ void cons_body(const Shape& s, const CUtensorMap* tmq
 template <int GATE, bool GD2, int FX>
 __global__ void __launch_bounds__(CT, 1)
     k_bwd_consumer_tc(Shape s, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                      const __grid_constant__ CUtensorMap tmo, const __grid_constant__ CUtensorMap tmg,
-                      const __grid_constant__ CUtensorMap tmv, const bf16* __restrict__ beta,
+                      const __grid_constant__ CUtensorMap tmo, const __grid_constant__ CUtensorMap tmv,
+                      const bf16* __restrict__ beta,
                       const float* __restrict__ g, Table t, FwdTC f, BwdTC bw, bf16* __restrict__ dq,
                       bf16* __restrict__ dk, bf16* __restrict__ dv, bf16* __restrict__ dbeta,
                       float* __restrict__ dg, Gdn2 gd, ConsPiece pc) {
@@ -1169,7 +1183,7 @@ __global__ void __launch_bounds__(CT, 1)
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tb = *tslot;
-    cons_body<GATE, GD2, FX>(s, &tmq, &tmk, &tmo, &tmg, &tmv, beta, g, t, f, bw, dq, dk, dv, dbeta, dg, gd, pc, base, tb);
+    cons_body<GATE, GD2, FX>(s, &tmq, &tmk, &tmo, &tmv, beta, g, t, f, bw, dq, dk, dv, dbeta, dg, gd, pc, base, tb);
     tc::fence_before_sync();
     __syncthreads();
     if (threadIdx.x < 32) tc::tmem_dealloc(tb, 512);
@@ -1183,8 +1197,8 @@ __global__ void __launch_bounds__(CT, 1)
 template <int GATE, bool GD2, int FX>
 __global__ void __launch_bounds__(CT, 1)
     k_bwd_joint_tc(Shape s, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                   const __grid_constant__ CUtensorMap tmo, const __grid_constant__ CUtensorMap tmg,
-                   const __grid_constant__ CUtensorMap tmv, const float* __restrict__ dht, float* __restrict__ dh0,
+                   const __grid_constant__ CUtensorMap tmo, const __grid_constant__ CUtensorMap tmv,
+                   const float* __restrict__ dht, float* __restrict__ dh0,
                    const bf16* __restrict__ beta, const float* __restrict__ g, Table t, FwdTC f, BwdTC bw,
                    bf16* __restrict__ dq, bf16* __restrict__ dk, bf16* __restrict__ dv, bf16* __restrict__ dbeta,
                    float* __restrict__ dg, Gdn2 gd, ConsPiece pc) {
@@ -1208,7 +1222,7 @@ __global__ void __launch_bounds__(CT, 1)
         __syncthreads();
         tc::fence_after_sync();
     }
-    cons_body<GATE, GD2, FX>(s, &tmq, &tmk, &tmo, &tmg, &tmv, beta, g, t, f, bw, dq, dk, dv, dbeta, dg, gd, pc, base, tb);
+    cons_body<GATE, GD2, FX>(s, &tmq, &tmk, &tmo, &tmv, beta, g, t, f, bw, dq, dk, dv, dbeta, dg, gd, pc, base, tb);
     tc::fence_before_sync();
     __syncthreads();
     if (threadIdx.x < 32) tc::tmem_dealloc(tb, 512);
@@ -1220,19 +1234,18 @@ cudaError_t run_consumer(const Shape& s, const void* q, const void* k, const voi
                          void* dv, void* dbeta, float* dg, cudaStream_t st, const Gdn2& gd, const ConsPiece& pc) {
     cudaError_t e = set_smem_once<k_bwd_consumer_tc<GATE, GD2, FX>>(CONS_SMEM);
     if (e != cudaSuccess) return e;
-    CUtensorMap mq, mk, mo, mg, mv;
-    memset(&mg, 0, sizeof(mg));
-    // the inputs at their own widths K, V (<= D): the boxes' columns past them read as zeros
-    // (q, k with heads_q(s) heads, g with heads_g(s))
+    CUtensorMap mq, mk, mo, mv;
+    // the inputs at their own widths K, V (<= D): the boxes' columns past them read as zeros (q, k
+    // with heads_q(s) heads; a per-channel gate reaches the consumer as the prep's alpha rows)
     if (!tmap_rows_bf16(&mq, q, s.Ttot, heads_q(s), s.K) || !tmap_rows_bf16(&mk, k, s.Ttot, heads_q(s), s.K) ||
-        !tmap_rows_bf16(&mo, dout, s.Ttot, s.H, s.V) || !tmap_rows_bf16(&mv, v, s.Ttot, s.H, s.V) ||
-        (GATE == 2 && !tmap_rows_f32(&mg, g, s.Ttot, heads_g(s), s.K, D)))
+        !tmap_rows_bf16(&mo, dout, s.Ttot, s.H, s.V) || !tmap_rows_bf16(&mv, v, s.Ttot, s.H, s.V))
         return cudaErrorInvalidValue;
+    if (GATE == 2 && !f.ALK) return cudaErrorInvalidValue;
     const long units = pc.L ? (long)s.N * pc.L * s.H : (long)s.NC * s.H;
     if (units <= 0) return cudaSuccess;
     if (units > 0x7fffffffL) return cudaErrorInvalidValue;
     const int grid = (int)(units < sm_count() ? units : sm_count());   // one CTA per SM, persistent
-    k_bwd_consumer_tc<GATE, GD2, FX><<<grid, CT, CONS_SMEM, st>>>(s, mq, mk, mo, mg, mv, (const bf16*)beta, g, t, f, b,
+    k_bwd_consumer_tc<GATE, GD2, FX><<<grid, CT, CONS_SMEM, st>>>(s, mq, mk, mo, mv, (const bf16*)beta, g, t, f, b,
                                                          (bf16*)dq, (bf16*)dk, (bf16*)dv, (bf16*)dbeta, dg, gd, pc);
     return cudaGetLastError();
 }
@@ -1243,14 +1256,13 @@ cudaError_t run_joint(const Shape& s, const void* q, const void* k, const void* 
                       void* dv, void* dbeta, float* dg, cudaStream_t st, const Gdn2& gd, const ConsPiece& pc) {
     cudaError_t e = set_smem_once<k_bwd_joint_tc<GATE, GD2, FX>>(JOINT_SMEM);
     if (e != cudaSuccess) return e;
-    CUtensorMap mq, mk, mo, mg, mv;
-    memset(&mg, 0, sizeof(mg));
-    // the inputs at their own widths K, V (<= D): the boxes' columns past them read as zeros
-    // (q, k with heads_q(s) heads, g with heads_g(s))
+    CUtensorMap mq, mk, mo, mv;
+    // the inputs at their own widths K, V (<= D): the boxes' columns past them read as zeros (q, k
+    // with heads_q(s) heads; a per-channel gate reaches the consumer as the prep's alpha rows)
     if (!tmap_rows_bf16(&mq, q, s.Ttot, heads_q(s), s.K) || !tmap_rows_bf16(&mk, k, s.Ttot, heads_q(s), s.K) ||
-        !tmap_rows_bf16(&mo, dout, s.Ttot, s.H, s.V) || !tmap_rows_bf16(&mv, v, s.Ttot, s.H, s.V) ||
-        (GATE == 2 && !tmap_rows_f32(&mg, g, s.Ttot, heads_g(s), s.K, D)))
+        !tmap_rows_bf16(&mo, dout, s.Ttot, s.H, s.V) || !tmap_rows_bf16(&mv, v, s.Ttot, s.H, s.V))
         return cudaErrorInvalidValue;
+    if (GATE == 2 && !f.ALK) return cudaErrorInvalidValue;
     const int grid = sm_count();
     if (s.N * s.H > grid || !pc.flags || !pc.ctr) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
@@ -1263,7 +1275,7 @@ cudaError_t run_joint(const Shape& s, const void* q, const void* k, const void* 
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_bwd_joint_tc<GATE, GD2, FX>, s, mq, mk, mo, mg, mv, dht, dh0, (const bf16*)beta, g,
+    return cudaLaunchKernelEx(&cfg, k_bwd_joint_tc<GATE, GD2, FX>, s, mq, mk, mo, mv, dht, dh0, (const bf16*)beta, g,
                               t, f, b, (bf16*)dq, (bf16*)dk, (bf16*)dv, (bf16*)dbeta, dg, gd, pc);
 }
 

@@ -280,12 +280,24 @@ __global__ void __launch_bounds__(PT, 2)
         hi = fmaxf(sHi[col], sHi[D + col]);
         lo = fminf(sLo[col], sLo[D + col]);
         const float cc = 0.5f * (hi + lo);
+        // saving for the backward with a per-channel gate: alpha as token rows (coalesced), then
+        // 2^c and 2^(G2_last - c), for the backward consumer to load in place of g
+        float* img = (BWD && GATE == 2) ? f.ALK + ch * ALK_UNIT : nullptr;
 #pragma unroll
-        for (int r = 0; r < 32; ++r) sA[(32 * seg + r) * LG + col] = exp2f(x[r] - cc);
+        for (int r = 0; r < 32; ++r) {
+            const float a = exp2f(x[r] - cc);
+            sA[(32 * seg + r) * LG + col] = a;
+            if (BWD && GATE == 2) img[(32 * seg + r) * D + col] = a;
+        }
         if (seg == 1) {   // G2 at row 63 = last token
-            sC2[col] = exp2f(cc);
-            sAL[col] = exp2f(x[31] - cc);
+            const float c2 = exp2f(cc), al = exp2f(x[31] - cc);
+            sC2[col] = c2;
+            sAL[col] = al;
             f.GL[ch * D + col] = x[31];
+            if (BWD && GATE == 2) {
+                img[BT * D + col] = c2;
+                img[BT * D + D + col] = al;
+            }
         }
         wide_col = (hi - lo) > PREP_RANGE_LOG2;
     }

@@ -68,7 +68,8 @@ def test_workspace_size_arithmetic():
     # bf16 W, F, Q_g, U tiles, C_q; fp32 gate at the chunk end; wide flags and list
     ftc = up(2 * chd * BT * D) * 4 + up(2 * chd * BT * BT) + up(4 * chd * D) + up(4 * chd) + up(4 * (chd + 1))
     assert _ws(ptc, 0) == table + ftc
-    ftc_b = up(2 * chd * BT * BT) + up(2 * chd * D * D) + up(2 * chd * BT * D)
+    # saved for the backward: A, S, R and, with a per-channel gate, alpha and two rows of 128 per unit
+    ftc_b = up(2 * chd * BT * BT) + up(2 * chd * D * D) + up(2 * chd * BT * D) + up(4 * chd * (BT * D + 2 * D))
     btc = up(2 * chd * D * D) + up(2 * chd * BT * D)
     wscr = up(4 * chd * BT * D) * 3 + up(4 * chd * BT * BT) * 2 + up(4 * chd * D) + up(4 * chd * BT)
     # equal-length batches: two fp32 state adjoints and eight claim counters for a backward in time
@@ -79,6 +80,9 @@ def test_workspace_size_arithmetic():
     assert _ws(ptca, 0) == table
     assert _ws(ptca, 1) == table + btc + wscr + piece
     assert _lib.load().kda_saved_size(ctypes.byref(ptca)) == ftc + ftc_b
+    # a scalar gate saves no alpha (its backward takes the cumsum of one value per token)
+    assert _lib.load().kda_saved_size(ctypes.byref(_prob(io=0, save=1, gate=1))) == \
+        ftc + ftc_b - up(4 * chd * (BT * D + 2 * D))
     pa = _prob(save=1, io=1)
     assert _ws(pa, 0) == table
     assert _ws(pa, 1) == table + bwd
