@@ -82,13 +82,15 @@ def kernel_work(case, save=False):
     must read or write once at its stored precision, the chunk intermediates
     included), summed over chunk x head with the exact chunk length n
     (d = dk = dv). Under the save policy the forward prep also writes A for the
-    backward and, with a per-channel gate, alpha (fp32 token rows and two rows
-    of d), which the consumer reads in place of g. The roofline's algorithmic
+    backward and alpha with its two constants (per-channel gate: fp32 token rows
+    and two rows of d; scalar gate: 80 floats), which the consumer reads in
+    place of g. The roofline's algorithmic
     bytes (the operator's own inputs, outputs and states only) are in io_bytes."""
     d = case.K
     e = 2 if case.io == "bf16" else 4
     gb = {"channel": 4 * d, "scalar": 4, "none": 0}[case.gate]   # log-decay bytes per token
-    ga = 2 * d * 4 if case.gate == "channel" else 0   # the alpha rows' 2^c and 2^(G2_last - c)
+    # alpha saved for the consumer per chunk x head (fp32), in place of its g
+    alpha = {"channel": 64 * d * 4 + 2 * d * 4, "scalar": 80 * 4, "none": 0}[case.gate]
     fl = dict(k_prep=0.0, k_fwd_scan=0.0, k_fwd_scan_recompute=0.0, k_bwd_scan=0.0,
               k_bwd_dstate=0.0, k_bwd_intra=0.0, k_prep_tc=0.0, k_fwd_scan_tc=0.0,
               k_fwd_scan_tc_recompute=0.0, k_fwd_scan_tc_save=0.0, k_bwd_scan_tc=0.0, k_bwd_consumer_tc=0.0)
@@ -108,12 +110,12 @@ def kernel_work(case, save=False):
         fl["k_bwd_consumer_tc"] += 12 * n * n * d + 6 * n * d * d
         # tensor-core path: bf16 tiles W, U, F, Q_g, C_q, A, S, S+bar, R, P; fp32 G at the chunk end
         by["k_prep_tc"] += (3 * n * d * e + n * gb + n * e + 4 * n * d * 2 + n * n * 2 + d * 4
-                            + ((n * n * 2 + (n * gb + ga if ga else 0)) if save else 0))
+                            + ((n * n * 2 + alpha) if save else 0))
         by["k_fwd_scan_tc"] += 4 * n * d * 2 + n * n * 2 + d * 4 + n * d * e
         by["k_fwd_scan_tc_recompute"] += 3 * n * d * 2 + d * 4 + d * d * 2 + n * d * 2
         by["k_fwd_scan_tc_save"] += 3 * n * d * 2 + d * 4 + d * d * 2 + n * d * 2
         by["k_bwd_scan_tc"] += 3 * n * d * 2 + 2 * n * n * 2 + d * 4 + n * d * e + d * d * 2 + n * d * 2
-        by["k_bwd_consumer_tc"] += (3 * n * d * 2 + 2 * d * d * 2 + 3 * n * d * e + n * gb + ga + n * e
+        by["k_bwd_consumer_tc"] += (3 * n * d * 2 + 2 * d * d * 2 + 3 * n * d * e + alpha + n * e
                                     + 3 * n * d * e + n * e + n * gb)
     st = 2 * 4 * d * d * case.N   # initial/final state (or its adjoint) per sequence, read + write
     for kname in ("k_fwd_scan_tc", "k_bwd_scan_tc"):
@@ -127,8 +129,8 @@ def kernel_work(case, save=False):
 def io_bytes(case):
     """Algorithmic HBM bytes per launch of each library kernel: only the operator's own inputs,
     outputs and states that the kernel reads or writes (chunk intermediates excluded), summed over
-    chunk x head with the exact chunk length n. The consumer reads q, k, v, dO, beta (and g for a
-    scalar gate: a per-channel gate reaches it as the prep's alpha, an intermediate) and writes
+    chunk x head with the exact chunk length n. The consumer reads q, k, v, dO, beta (the gate
+    reaches it as the prep's alpha, an intermediate) and writes
     dq, dk, dv, dbeta, dg; the prep reads q, k, v, beta, g; the output scan writes o and reads h0,
     writes ht; the reverse scan reads dO and dht and writes dh0."""
     d = case.K
@@ -142,7 +144,7 @@ def io_bytes(case):
         "k_fwd_scan_tc_save": st,
         "k_fwd_scan_tc_recompute": st,
         "k_bwd_scan_tc": tok * d * e + 2 * st,
-        "k_bwd_consumer_tc": tok * (4 * d * e + e + (0 if case.gate == "channel" else gb) + 3 * d * e + e + gb),
+        "k_bwd_consumer_tc": tok * (4 * d * e + e + 3 * d * e + e + gb),
     }
     # the joint schedule: the consumer's inputs and outputs plus the reverse scan's states (dO once)
     by["k_bwd_joint_tc"] = by["k_bwd_consumer_tc"] + 2 * st

@@ -23,7 +23,7 @@ struct Dims {
     int N = 0, NC = 0, Ttot = 0, H = 0;
     int D = 0, V = 0;   // key and value widths of the problem
     int WD = 0;         // working width of the chunk intermediates (the tile width of the path)
-    bool alk = false;   // per-channel gate: the tensor-core prep saves alpha for the backward consumer
+    int alk = 0;        // floats per chunk x head of the alpha the tensor-core prep saves for the backward
     int per = 0;        // chunks per sequence of an equal-length batch (0: packed sequences)
 };
 
@@ -67,7 +67,7 @@ kda_status check_dims(const kda_problem* p, Dims& d) {
     // CUDA-core path's problems are padded to K = V = 64, 128 or 256 before they get here)
     d.WD = (p->io == KDA_BF16 && p->K <= 128 && p->V <= 128) ? 128 : p->K;
     d.H = p->H;
-    d.alk = p->gate == KDA_GATE_CHANNEL;
+    d.alk = p->gate == KDA_GATE_CHANNEL ? kda::ALK_UNIT : p->gate == KDA_GATE_SCALAR ? kda::ALK_SCALAR : 0;
     const long long per = (p->T + kda::BT - 1) / kda::BT;
     if (p->cu_seqlens) {
         if (p->B != 1) return fail(KDA_ERR_INVALID_ARG, "packed sequences need B == 1");
@@ -108,7 +108,7 @@ Layout layout(const Dims& d) {
             up(4 * chd * D) + up(4 * chd * BT);
     L.ftc = up(2 * chd * BT * D) * 4 + up(2 * chd * BT * BT) + up(4 * chd * D) + up(4 * chd) + up(4 * (chd + 1));
     L.ftc_b = up(2 * chd * BT * BT) + up(2 * chd * D * D) + up(2 * chd * BT * D) +
-              (d.alk ? up(4 * chd * kda::ALK_UNIT) : 0);
+              (d.alk ? up(4 * chd * (size_t)d.alk) : 0);
     L.btc = up(2 * chd * D * D) + up(2 * chd * BT * D);
     L.wscr = up(4 * chd * BT * D) * 3 + up(4 * chd * BT * BT) * 2 + up(4 * chd * D) + up(4 * chd * BT);
     if (d.per) L.piece = 2 * up(4 * N * H * (size_t)d.D * d.V) + up(4 * kda::MAX_PIECES) + up(4 * chd);
@@ -183,7 +183,7 @@ void carve_fwd_tc(Carver& c, const Dims& d, kda::FwdTC& f, bool bwd_arrays) {
         f.AI = c.take<__nv_bfloat16>(2 * chd * BT * BT);
         f.HS = c.take<__nv_bfloat16>(2 * chd * D * D);
         f.R = c.take<__nv_bfloat16>(2 * chd * BT * D);
-        if (d.alk) f.ALK = c.take<float>(4 * chd * kda::ALK_UNIT);
+        if (d.alk) f.ALK = c.take<float>(4 * chd * (size_t)d.alk);
     }
 }
 
@@ -785,7 +785,7 @@ static kda_status chunk_bwd_core(const kda_problem* p, const void* dout, const f
             pc.per = d.per;
             pc.ctr = ctr;
             pc.flags = flags;
-            e = traced("k_bwd_joint_tc", cs, [&] { return kda::launch_bwd_joint_tc(s, gate, p->q, p->k, p->v, p->beta, p->g, dout, dht, dh0, t, f, b, dq, dk, dv, dbeta, dg, cs, gd, pc); });
+            e = traced("k_bwd_joint_tc", cs, [&] { return kda::launch_bwd_joint_tc(s, gate, p->q, p->k, p->v, p->beta, dout, dht, dh0, t, f, b, dq, dk, dv, dbeta, dg, cs, gd, pc); });
             if (e != cudaSuccess) return cuda_fail(e, "joint scan and consumer");
             e = traced("k_bwd_wide", cs, [&] { return gate == KDA_GATE_NONE ? cudaSuccess : kda::launch_bwd_wide(s, gate, p->q, p->k, p->v, p->beta, p->g, dout, t, f, b, scr, dq, dk, dv, dbeta, dg, cs, gd); });
             if (e != cudaSuccess) return cuda_fail(e, "consumer (wide chunks)");
@@ -801,7 +801,7 @@ static kda_status chunk_bwd_core(const kda_problem* p, const void* dout, const f
             e = traced("k_bwd_scan_tc", cs, [&] { return kda::launch_bwd_scan_tc(s, dout, dht, t, f, b, dh0, cs); });
             if (e != cudaSuccess) return cuda_fail(e, "reverse scan");
             if (sd && (e = side_join(sd, cs)) != cudaSuccess) return cuda_fail(e, "side stream");
-            e = traced("k_bwd_consumer_tc", cs, [&] { return kda::launch_bwd_consumer_tc(s, gate, p->q, p->k, p->v, p->beta, p->g, dout, t, f, b, dq, dk, dv, dbeta, dg, cs, gd); });
+            e = traced("k_bwd_consumer_tc", cs, [&] { return kda::launch_bwd_consumer_tc(s, gate, p->q, p->k, p->v, p->beta, dout, t, f, b, dq, dk, dv, dbeta, dg, cs, gd); });
             if (e != cudaSuccess) return cuda_fail(e, "consumer");
         } else {
             // time pieces: the scan of piece q+1 (main stream) runs beside the consumer of piece q (side
@@ -821,7 +821,7 @@ static kda_status chunk_bwd_core(const kda_problem* p, const void* dout, const f
                 e = traced("k_bwd_scan_tc", cs, [&] { return kda::launch_bwd_scan_tc(s, dout, din, t, f, b, dnext, cs, pc); });
                 if (e != cudaSuccess) return cuda_fail(e, "reverse scan");
                 if ((e = side_fork(sd, cs)) != cudaSuccess) return cuda_fail(e, "side stream");
-                e = traced("k_bwd_consumer_tc", sd->st, [&] { return kda::launch_bwd_consumer_tc(s, gate, p->q, p->k, p->v, p->beta, p->g, dout, t, f, b, dq, dk, dv, dbeta, dg, sd->st, gd, pc); });
+                e = traced("k_bwd_consumer_tc", sd->st, [&] { return kda::launch_bwd_consumer_tc(s, gate, p->q, p->k, p->v, p->beta, dout, t, f, b, dq, dk, dv, dbeta, dg, sd->st, gd, pc); });
                 if (e != cudaSuccess) return cuda_fail(e, "consumer");
             }
             if ((e = side_join(sd, cs)) != cudaSuccess) return cuda_fail(e, "side stream");

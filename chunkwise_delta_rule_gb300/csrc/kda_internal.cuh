@@ -92,15 +92,17 @@ struct FwdTC {
     int32_t* WLIST;       // [1 + NC*H]   count, then chunk slot * H + head of every WIDE chunk
     // backward-only (null in the forward)
     __nv_bfloat16* AI;    // [NC,H,BT,BT] A = (I + L)^-1
-    float* ALK;           // [NC,H][ALK_UNIT] per-channel gate: alpha = 2^(G2 - c) as the backward
-                          // consumer holds it (key-major rows of BT tokens, 16-byte groups swizzled
-                          // by key), then 2^c and 2^(G2_last - c) per key
+    float* ALK;           // alpha = 2^(G2 - c) and 2^c, 2^(G2_last - c) for the backward consumer:
+                          // per-channel gate [NC,H][ALK_UNIT] (fp32 token rows of 128, then a row of
+                          // each per key); scalar gate [NC,H][ALK_SCALAR] (per token, then the two)
     __nv_bfloat16* HS;    // [NC,H,D,D]   state entering the chunk, [key][value]
     __nv_bfloat16* R;     // [NC,H,BT,D]  corrections
 };
 
-// Floats per (chunk, head) of FwdTC::ALK: the [128][BT] alpha image and two rows of 128.
+// Floats per (chunk, head) of FwdTC::ALK: per-channel gate, alpha as [BT][128] token rows and two
+// rows of 128; scalar gate, BT alphas and the two constants (padded to 16 bytes).
 constexpr int ALK_UNIT = 128 * BT + 2 * 128;
+constexpr int ALK_SCALAR = BT + 16;
 
 // Backward intermediates of the tensor-core path (bf16, [row][col] as named).
 struct BwdTC {
@@ -431,11 +433,11 @@ cudaError_t launch_bwd_scan_tc(const Shape& s, const void* dout, const float* dh
 // The joint schedule: reverse scans and consumer in one cooperative launch of one CTA per SM
 // (N * H at most the SM count; pc.per, pc.ctr and pc.flags set, ctr and flags zeroed before the launch).
 cudaError_t launch_bwd_joint_tc(const Shape& s, int gate, const void* q, const void* k, const void* v,
-                                const void* beta, const float* g, const void* dout, const float* dht, float* dh0,
+                                const void* beta, const void* dout, const float* dht, float* dh0,
                                 Table t, FwdTC f, BwdTC b, void* dq, void* dk, void* dv, void* dbeta, float* dg,
                                 cudaStream_t st, const Gdn2& gd, const ConsPiece& pc);
 cudaError_t launch_bwd_consumer_tc(const Shape& s, int gate, const void* q, const void* k, const void* v,
-                                   const void* beta, const float* g, const void* dout, Table t, FwdTC f,
+                                   const void* beta, const void* dout, Table t, FwdTC f,
                                    BwdTC b, void* dq, void* dk, void* dv, void* dbeta, float* dg,
                                    cudaStream_t st, const Gdn2& gd = Gdn2{}, const ConsPiece& pc = ConsPiece{});
 // CUDA-core consumers for the WIDE chunks of the tensor-core path (reading its

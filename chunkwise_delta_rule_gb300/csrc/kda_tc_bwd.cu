@@ -424,8 +424,8 @@ constexpr int X_EQ = 0;          // [E_a^T | Q_a^T] tf32 [128][128] 64 KB   (row
 constexpr int X_DH = 65536;      // [D ; H_q]^T     tf32 [64][128]   32 KB   (rows token j, K = i')
 constexpr int X_BT = 98304;      // [D ; H_q]       tf32 [128][64]   32 KB   (rows i', K = token j)
 constexpr int X_END = 131072;
-constexpr int X_STG = X_END;     // per-warp staging of the transposed bf16 stores, 16 x 512 B
-constexpr int X_SCR = X_END;     // cumsum at the unit start: segment totals, maxima, minima [3][4][128] fp32
+constexpr int X_STG = X_END;     // per-warp staging of the transposed bf16 stores, 16 x 512 B; from the
+                                 // next unit's group C to its alpha pass, a scalar gate's alphas
 constexpr int C_A = X_STG + 16 * 512;             // g (dense rows, as TMA lands them), then alpha
                                                   // = 2^(G2 - c) at aidx(row, col), fp32 [64][128]
 constexpr int C_K = C_A + 4 * BT * D;             // k bf16 [64][128], SW128 rows
@@ -439,7 +439,7 @@ constexpr int CONS_SMEM = C_BAR + 64 + 1024;
 // token j): S dO^T, S P^T, F_bar^T, T_e^T, T_q^T, T_y^T; (K zeta)^T is the A operand of [T_e ; T_q]^T
 constexpr int T_HD = 0, T_SDO = 64, T_SP = 128, T_FB = 192, T_TE = 256, T_TQ = 320, T_Y = 384, T_KZ = 448;
 static_assert(X_V + BT * D * 2 <= X_END && X_BT + 2 * BT * BT * 4 <= X_END && X_DH + BT * D * 4 <= X_BT, "X region");
-static_assert(X_SCR + 12 * D * 4 <= C_A && X_STG + 16 * 512 <= C_A, "staging region");
+static_assert(X_STG + 16 * 512 <= C_A && 4 * ALK_SCALAR <= 16 * 512, "staging region");
 static_assert(X_OP % 1024 == 0 && X_V % 1024 == 0 && X_SB % 1024 == 0 && X_DH % 1024 == 0 && X_BT % 1024 == 0 &&
               C_A % 1024 == 0 && C_K % 1024 == 0 && C_Q % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 static_assert(CONS_SMEM <= 232448, "consumer shared memory above the per-block limit");
@@ -527,12 +527,13 @@ __device__ __forceinline__ int cons_find(int& i, int units, const ConsPiece& pc,
     return -1;
 }
 
-// Load group C of unit ch from tok0: k, q of head hq by TMA in SW128 rows; per-channel gate: the
-// prep's alpha (fp32 token rows) and its 2^c, 2^(G2_last - c) rows as they are.
+// Load group C of unit ch from tok0: k, q of head hq by TMA in SW128 rows, and the prep's alpha
+// as it is: per-channel gate, fp32 token rows into the alpha tile and its 2^c, 2^(G2_last - c)
+// rows into theirs; scalar gate, the BT alphas and two constants into the staging region.
 template <int GATE>
 __device__ __forceinline__ void cons_load_c(uint32_t sb, const CUtensorMap* tmk, const CUtensorMap* tmq,
                                             const FwdTC& f, size_t ch, int hq, int tok0, uint64_t* b) {
-    tc::mbar_arrive_expect_tx(b, 2 * BT * D * 2 + (GATE == 2 ? 4 * ALK_UNIT : 0));
+    tc::mbar_arrive_expect_tx(b, 2 * BT * D * 2 + (GATE == 2 ? 4 * ALK_UNIT : GATE == 1 ? 4 * ALK_SCALAR : 0));
     tc::tma_load3(sb + C_K, tmk, 0, hq, tok0, b);
     tc::tma_load3(sb + C_K + 8192, tmk, 64, hq, tok0, b);
     tc::tma_load3(sb + C_Q, tmq, 0, hq, tok0, b);
@@ -541,6 +542,8 @@ __device__ __forceinline__ void cons_load_c(uint32_t sb, const CUtensorMap* tmk,
         const float* img = f.ALK + ch * ALK_UNIT;
         tc::bulk_g2s(sb + C_A, img, 4 * BT * D, b);
         tc::bulk_g2s(sb + C_MISC + 4 * M_C2, img + BT * D, 4 * 2 * D, b);
+    } else if (GATE == 1) {
+        tc::bulk_g2s(sb + X_STG, f.ALK + ch * ALK_SCALAR, 4 * ALK_SCALAR, b);
     }
 }
 
@@ -593,7 +596,7 @@ __device__ __forceinline__ bool cons_wait(uint64_t* b, int& w, int32_t* err) {
 template <int GATE, bool GD2, int FX>
 __device__ __forceinline__ void cons_body(const Shape& s, const CUtensorMap* tmq_, const CUtensorMap* tmk_,
                                           const CUtensorMap* tmo_, const CUtensorMap* tmv_,
-                                          const bf16* __restrict__ beta, const float* __restrict__ g, const Table& t,
+                                          const bf16* __restrict__ beta, const Table& t,
                                           const FwdTC& f, const BwdTC& bw, bf16* __restrict__ dq,
                                           bf16* __restrict__ dk, bf16* __restrict__ dv, bf16* __restrict__ dbeta,
                                           float* __restrict__ dg, const Gdn2& gd, const ConsPiece& pc,
@@ -683,14 +686,6 @@ __device__ __forceinline__ void cons_body(const Shape& s, const CUtensorMap* tmq
         const float beta_r =
             (k == 0) ? ((tid < BT && tid < n && !GD2) ? bfx(beta + (size_t)(tok0 + tid) * Hg + (FX ? h / s.Gg : h)) : 0.f)
                      : __bfloat162float(beta_nx);
-        // the G tile for a scalar gate (or zeros): tile C_A is free since the previous unit's epilogue
-        if (GATE != 2) {
-            for (int idx = tid; idx < BT * D / 4; idx += CT) {
-                const int r = idx >> 5, c4 = (idx & 31) * 4;
-                const float x = (GATE == 1 && r < n) ? __ldg(g + (size_t)(tok0 + r) * Hg + (FX ? h / s.Gg : h)) : 0.f;
-                *reinterpret_cast<float4*>(sA + r * D + c4) = make_float4(x, x, x, x);
-            }
-        }
         if (tid < BT) sBeta[tid] = beta_r;
         // groups X1 and X2: [R ; S], S+bar, [dO ; P], v
         {
@@ -815,11 +810,10 @@ __device__ __forceinline__ void cons_body(const Shape& s, const CUtensorMap* tmq
             }
         }
         // alpha of this thread's key kr and rows jb .. jb+15 (the same key and tokens it handles in
-        // every later pass). Per-channel gate: the prep's, as token rows. Otherwise the cumsum (4
-        // segments of 16 rows per feature, meeting in shared memory), the midpoint anchor and
-        // alpha = 2^(G2 - c). alpha, k and q are then rewritten key-major over their own tiles.
+        // every later pass): the prep's (per-channel gate: token rows in the alpha tile; scalar gate:
+        // one per token in the staging region), or 1 without a gate. alpha, k and q are then
+        // rewritten key-major over their own tiles.
         {
-            float* xt = reinterpret_cast<float*>(base + X_SCR);   // [3][4][128] totals, maxima, minima
             uint32_t kk[8], qq[8];   // k and q of this key for the 16 rows, bf16 pairs
 #pragma unroll
             for (int r = 0; r < 16; r += 2) {
@@ -829,46 +823,15 @@ __device__ __forceinline__ void cons_body(const Shape& s, const CUtensorMap* tmq
                 qq[r / 2] = (uint32_t)*reinterpret_cast<const uint16_t*>(sQ + o0) |
                             ((uint32_t)*reinterpret_cast<const uint16_t*>(sQ + o1) << 16);
             }
+            const float* sAs = reinterpret_cast<const float*>(base + X_STG);   // scalar gate: [BT] alpha, 2^c, 2^(G2_last - c)
             float x[16];
-            float acc = 0.f, hi = -INFINITY, lo = INFINITY;
 #pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                const int row = jb + r;
-                if (GATE == 2) {
-                    x[r] = sA[row * D + kr];
-                } else {
-                    acc += (row < n) ? sA[row * D + kr] : 0.f;
-                    x[r] = acc * LOG2E;
-                    if (row < n) {
-                        hi = fmaxf(hi, x[r]);
-                        lo = fminf(lo, x[r]);
-                    }
-                }
+            for (int r = 0; r < 16; ++r) x[r] = GATE == 2 ? sA[(jb + r) * D + kr] : GATE == 1 ? sAs[jb + r] : 1.f;
+            if (GATE != 2 && grp == 0) {
+                sC2[kr] = GATE == 1 ? sAs[BT] : 1.f;
+                sAL[kr] = GATE == 1 ? sAs[BT + 1] : 1.f;
             }
-            if (GATE != 2) {
-                xt[grp * D + kr] = acc * LOG2E;
-                xt[4 * D + grp * D + kr] = hi;
-                xt[8 * D + grp * D + kr] = lo;
-            }
-            __syncthreads();   // (also: every alpha (or g), k, q read before the key-major tiles overwrite them)
-            if (GATE != 2) {
-                float off = 0.f, run = 0.f, hh = -INFINITY, ll = INFINITY;
-#pragma unroll
-                for (int s2 = 0; s2 < 4; ++s2) {
-                    const float ts = xt[s2 * D + kr];
-                    if (s2 < grp) off = run + ts;
-                    hh = fmaxf(hh, xt[4 * D + s2 * D + kr] + run);
-                    ll = fminf(ll, xt[8 * D + s2 * D + kr] + run);
-                    run += ts;
-                }
-                const float cc = (GATE == 0) ? 0.f : 0.5f * (hh + ll);
-#pragma unroll
-                for (int r = 0; r < 16; ++r) x[r] = exp2f(x[r] + off - cc);
-                if (grp == 0) {
-                    sC2[kr] = exp2f(cc);
-                    sAL[kr] = exp2f(run - cc);   // run: G2 at the chunk end
-                }
-            }
+            __syncthreads();   // (also: every alpha, k, q read before the key-major tiles overwrite them)
 #pragma unroll
             for (int m = 0; m < 4; ++m)
                 *reinterpret_cast<float4*>(sA + akm4(kr, 4 * grp + m)) =
@@ -1168,7 +1131,7 @@ __global__ void __launch_bounds__(CT, 1)
     k_bwd_consumer_tc(Shape s, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmo, const __grid_constant__ CUtensorMap tmv,
                       const bf16* __restrict__ beta,
-                      const float* __restrict__ g, Table t, FwdTC f, BwdTC bw, bf16* __restrict__ dq,
+                      Table t, FwdTC f, BwdTC bw, bf16* __restrict__ dq,
                       bf16* __restrict__ dk, bf16* __restrict__ dv, bf16* __restrict__ dbeta,
                       float* __restrict__ dg, Gdn2 gd, ConsPiece pc) {
     extern __shared__ unsigned char smem_raw[];
@@ -1183,7 +1146,7 @@ __global__ void __launch_bounds__(CT, 1)
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tb = *tslot;
-    cons_body<GATE, GD2, FX>(s, &tmq, &tmk, &tmo, &tmv, beta, g, t, f, bw, dq, dk, dv, dbeta, dg, gd, pc, base, tb);
+    cons_body<GATE, GD2, FX>(s, &tmq, &tmk, &tmo, &tmv, beta, t, f, bw, dq, dk, dv, dbeta, dg, gd, pc, base, tb);
     tc::fence_before_sync();
     __syncthreads();
     if (threadIdx.x < 32) tc::tmem_dealloc(tb, 512);
@@ -1199,7 +1162,7 @@ __global__ void __launch_bounds__(CT, 1)
     k_bwd_joint_tc(Shape s, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmo, const __grid_constant__ CUtensorMap tmv,
                    const float* __restrict__ dht, float* __restrict__ dh0,
-                   const bf16* __restrict__ beta, const float* __restrict__ g, Table t, FwdTC f, BwdTC bw,
+                   const bf16* __restrict__ beta, Table t, FwdTC f, BwdTC bw,
                    bf16* __restrict__ dq, bf16* __restrict__ dk, bf16* __restrict__ dv, bf16* __restrict__ dbeta,
                    float* __restrict__ dg, Gdn2 gd, ConsPiece pc) {
     extern __shared__ unsigned char smem_raw[];
@@ -1222,7 +1185,7 @@ __global__ void __launch_bounds__(CT, 1)
         __syncthreads();
         tc::fence_after_sync();
     }
-    cons_body<GATE, GD2, FX>(s, &tmq, &tmk, &tmo, &tmv, beta, g, t, f, bw, dq, dk, dv, dbeta, dg, gd, pc, base, tb);
+    cons_body<GATE, GD2, FX>(s, &tmq, &tmk, &tmo, &tmv, beta, t, f, bw, dq, dk, dv, dbeta, dg, gd, pc, base, tb);
     tc::fence_before_sync();
     __syncthreads();
     if (threadIdx.x < 32) tc::tmem_dealloc(tb, 512);
@@ -1230,7 +1193,7 @@ __global__ void __launch_bounds__(CT, 1)
 
 template <int GATE, bool GD2, int FX>
 cudaError_t run_consumer(const Shape& s, const void* q, const void* k, const void* v, const void* beta,
-                         const float* g, const void* dout, Table t, FwdTC f, BwdTC b, void* dq, void* dk,
+                         const void* dout, Table t, FwdTC f, BwdTC b, void* dq, void* dk,
                          void* dv, void* dbeta, float* dg, cudaStream_t st, const Gdn2& gd, const ConsPiece& pc) {
     cudaError_t e = set_smem_once<k_bwd_consumer_tc<GATE, GD2, FX>>(CONS_SMEM);
     if (e != cudaSuccess) return e;
@@ -1240,18 +1203,18 @@ cudaError_t run_consumer(const Shape& s, const void* q, const void* k, const voi
     if (!tmap_rows_bf16(&mq, q, s.Ttot, heads_q(s), s.K) || !tmap_rows_bf16(&mk, k, s.Ttot, heads_q(s), s.K) ||
         !tmap_rows_bf16(&mo, dout, s.Ttot, s.H, s.V) || !tmap_rows_bf16(&mv, v, s.Ttot, s.H, s.V))
         return cudaErrorInvalidValue;
-    if (GATE == 2 && !f.ALK) return cudaErrorInvalidValue;
+    if (GATE != 0 && !f.ALK) return cudaErrorInvalidValue;
     const long units = pc.L ? (long)s.N * pc.L * s.H : (long)s.NC * s.H;
     if (units <= 0) return cudaSuccess;
     if (units > 0x7fffffffL) return cudaErrorInvalidValue;
     const int grid = (int)(units < sm_count() ? units : sm_count());   // one CTA per SM, persistent
-    k_bwd_consumer_tc<GATE, GD2, FX><<<grid, CT, CONS_SMEM, st>>>(s, mq, mk, mo, mv, (const bf16*)beta, g, t, f, b,
+    k_bwd_consumer_tc<GATE, GD2, FX><<<grid, CT, CONS_SMEM, st>>>(s, mq, mk, mo, mv, (const bf16*)beta, t, f, b,
                                                          (bf16*)dq, (bf16*)dk, (bf16*)dv, (bf16*)dbeta, dg, gd, pc);
     return cudaGetLastError();
 }
 
 template <int GATE, bool GD2, int FX>
-cudaError_t run_joint(const Shape& s, const void* q, const void* k, const void* v, const void* beta, const float* g,
+cudaError_t run_joint(const Shape& s, const void* q, const void* k, const void* v, const void* beta,
                       const void* dout, const float* dht, float* dh0, Table t, FwdTC f, BwdTC b, void* dq, void* dk,
                       void* dv, void* dbeta, float* dg, cudaStream_t st, const Gdn2& gd, const ConsPiece& pc) {
     cudaError_t e = set_smem_once<k_bwd_joint_tc<GATE, GD2, FX>>(JOINT_SMEM);
@@ -1262,7 +1225,7 @@ cudaError_t run_joint(const Shape& s, const void* q, const void* k, const void* 
     if (!tmap_rows_bf16(&mq, q, s.Ttot, heads_q(s), s.K) || !tmap_rows_bf16(&mk, k, s.Ttot, heads_q(s), s.K) ||
         !tmap_rows_bf16(&mo, dout, s.Ttot, s.H, s.V) || !tmap_rows_bf16(&mv, v, s.Ttot, s.H, s.V))
         return cudaErrorInvalidValue;
-    if (GATE == 2 && !f.ALK) return cudaErrorInvalidValue;
+    if (GATE != 0 && !f.ALK) return cudaErrorInvalidValue;
     const int grid = sm_count();
     if (s.N * s.H > grid || !pc.flags || !pc.ctr) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
@@ -1275,19 +1238,19 @@ cudaError_t run_joint(const Shape& s, const void* q, const void* k, const void* 
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_bwd_joint_tc<GATE, GD2, FX>, s, mq, mk, mo, mv, dht, dh0, (const bf16*)beta, g,
+    return cudaLaunchKernelEx(&cfg, k_bwd_joint_tc<GATE, GD2, FX>, s, mq, mk, mo, mv, dht, dh0, (const bf16*)beta,
                               t, f, b, (bf16*)dq, (bf16*)dk, (bf16*)dv, (bf16*)dbeta, dg, gd, pc);
 }
 
 }  // namespace
 
 cudaError_t launch_bwd_joint_tc(const Shape& s, int gate, const void* q, const void* k, const void* v,
-                                const void* beta, const float* g, const void* dout, const float* dht, float* dh0,
+                                const void* beta, const void* dout, const float* dht, float* dh0,
                                 Table t, FwdTC f, BwdTC b, void* dq, void* dk, void* dv, void* dbeta, float* dg,
                                 cudaStream_t st, const Gdn2& gd, const ConsPiece& pc) {
     // narrower inputs (and grouped heads with them), grouped heads at the tile width, or neither
     const int fx = (s.K != D || s.V != D) ? 2 : (s.Gq != 1 || s.Gg != 1) ? 1 : 0;
-#define KDA_JOINT_FX(G, X, F) run_joint<G, X, F>(s, q, k, v, beta, g, dout, dht, dh0, t, f, b, dq, dk, dv, dbeta, dg, st, gd, pc)
+#define KDA_JOINT_FX(G, X, F) run_joint<G, X, F>(s, q, k, v, beta, dout, dht, dh0, t, f, b, dq, dk, dv, dbeta, dg, st, gd, pc)
 #define KDA_JOINT(G, X) (fx == 2 ? KDA_JOINT_FX(G, X, 2) : fx == 1 ? KDA_JOINT_FX(G, X, 1) : KDA_JOINT_FX(G, X, 0))
     switch (gate) {
         case 0: return gd.erase ? KDA_JOINT(0, true) : KDA_JOINT(0, false);
@@ -1310,15 +1273,15 @@ cudaError_t launch_bwd_scan_tc(const Shape& s, const void* dout, const float* dh
 }
 
 cudaError_t launch_bwd_consumer_tc(const Shape& s, int gate, const void* q, const void* k, const void* v,
-                                   const void* beta, const float* g, const void* dout, Table t, FwdTC f,
+                                   const void* beta, const void* dout, Table t, FwdTC f,
                                    BwdTC b, void* dq, void* dk, void* dv, void* dbeta, float* dg,
                                    cudaStream_t st, const Gdn2& gd, const ConsPiece& pc) {
     // narrower inputs or grouped heads (the consumer's flexible variant keeps its registers at the
     // tile width too), or neither
     const bool flex = s.K != D || s.V != D || s.Gq != 1 || s.Gg != 1;
 #define KDA_CONS(G, X)                                                                                    \
-    (flex ? run_consumer<G, X, 2>(s, q, k, v, beta, g, dout, t, f, b, dq, dk, dv, dbeta, dg, st, gd, pc) \
-          : run_consumer<G, X, 0>(s, q, k, v, beta, g, dout, t, f, b, dq, dk, dv, dbeta, dg, st, gd, pc))
+    (flex ? run_consumer<G, X, 2>(s, q, k, v, beta, dout, t, f, b, dq, dk, dv, dbeta, dg, st, gd, pc) \
+          : run_consumer<G, X, 0>(s, q, k, v, beta, dout, t, f, b, dq, dk, dv, dbeta, dg, st, gd, pc))
     switch (gate) {
         case 0: return gd.erase ? KDA_CONS(0, true) : KDA_CONS(0, false);
         case 1: return gd.erase ? KDA_CONS(1, true) : KDA_CONS(1, false);

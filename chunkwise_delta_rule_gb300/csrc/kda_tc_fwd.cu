@@ -280,23 +280,25 @@ __global__ void __launch_bounds__(PT, 2)
         hi = fmaxf(sHi[col], sHi[D + col]);
         lo = fminf(sLo[col], sLo[D + col]);
         const float cc = 0.5f * (hi + lo);
-        // saving for the backward with a per-channel gate: alpha as token rows (coalesced), then
-        // 2^c and 2^(G2_last - c), for the backward consumer to load in place of g
-        float* img = (BWD && GATE == 2) ? f.ALK + ch * ALK_UNIT : nullptr;
+        // saving for the backward: alpha, 2^c and 2^(G2_last - c) for the backward consumer, which
+        // loads them in place of g (per-channel gate: token rows, coalesced over the features;
+        // scalar gate: the values of feature 0, equal for every feature)
+        float* img = (BWD && GATE != 0) ? f.ALK + ch * (GATE == 2 ? ALK_UNIT : ALK_SCALAR) : nullptr;
+        const bool put = BWD && (GATE == 2 || (GATE == 1 && col == 0));
 #pragma unroll
         for (int r = 0; r < 32; ++r) {
             const float a = exp2f(x[r] - cc);
             sA[(32 * seg + r) * LG + col] = a;
-            if (BWD && GATE == 2) img[(32 * seg + r) * D + col] = a;
+            if (put) img[(32 * seg + r) * (GATE == 2 ? D : 1) + (GATE == 2 ? col : 0)] = a;
         }
         if (seg == 1) {   // G2 at row 63 = last token
             const float c2 = exp2f(cc), al = exp2f(x[31] - cc);
             sC2[col] = c2;
             sAL[col] = al;
             f.GL[ch * D + col] = x[31];
-            if (BWD && GATE == 2) {
-                img[BT * D + col] = c2;
-                img[BT * D + D + col] = al;
+            if (put) {
+                img[BT * (GATE == 2 ? D : 1) + (GATE == 2 ? col : 0)] = c2;
+                img[BT * (GATE == 2 ? D : 1) + (GATE == 2 ? D + col : 1)] = al;
             }
         }
         wide_col = (hi - lo) > PREP_RANGE_LOG2;

@@ -80,9 +80,10 @@ def test_workspace_size_arithmetic():
     assert _ws(ptca, 0) == table
     assert _ws(ptca, 1) == table + btc + wscr + piece
     assert _lib.load().kda_saved_size(ctypes.byref(ptca)) == ftc + ftc_b
-    # a scalar gate saves no alpha (its backward takes the cumsum of one value per token)
-    assert _lib.load().kda_saved_size(ctypes.byref(_prob(io=0, save=1, gate=1))) == \
-        ftc + ftc_b - up(4 * chd * (BT * D + 2 * D))
+    # a scalar gate saves one alpha per token and its two constants (80 floats per unit), no gate none
+    alk = up(4 * chd * (BT * D + 2 * D))
+    assert _lib.load().kda_saved_size(ctypes.byref(_prob(io=0, save=1, gate=1))) == ftc + ftc_b - alk + up(4 * chd * 80)
+    assert _lib.load().kda_saved_size(ctypes.byref(_prob(io=0, save=1, gate=0))) == ftc + ftc_b - alk
     pa = _prob(save=1, io=1)
     assert _ws(pa, 0) == table
     assert _ws(pa, 1) == table + bwd
