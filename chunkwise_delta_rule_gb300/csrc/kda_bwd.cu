@@ -26,6 +26,8 @@
 namespace kda {
 namespace {
 
+using bf16 = __nv_bfloat16;
+
 constexpr int SL = 32;  // value columns of S per slice in k_bwd_dstate
 
 // IT: element type of the P, R, S and S+bar inputs: fp32 row-major here, bf16
@@ -534,83 +536,106 @@ __device__ __forceinline__ void intra_chunk(int c, int h, const Shape& s, const 
     }
 }
 
-// With a list (count, then chunk slot * H + head): only the listed chunks,
-// spread over a grid of one CTA per SM; without: one CTA per (chunk slot, head).
+// One CTA per (chunk slot, head).
 template <typename TI, typename IT, int D>
 __global__ void __launch_bounds__(NTHREADS, 1)
     k_bwd_dstate(Shape s, const TI* __restrict__ dout, const TI* __restrict__ v,
                  const TI* __restrict__ beta, Table t, const IT* __restrict__ Pin,
                  const IT* __restrict__ Rin, const IT* __restrict__ Sin, const IT* __restrict__ SBin,
-                 const int32_t* __restrict__ list, Bwd b, TI* __restrict__ dv, Gdn2 gd) {
-    if (list) {
-        const int cnt = list[0];
-        for (int w = blockIdx.x; w < cnt; w += gridDim.x) {
-            const int ch = list[1 + w];
-            dstate_chunk<TI, IT, D>(ch / s.H, ch % s.H, s, dout, v, beta, t, Pin, Rin, Sin, SBin, b, dv, gd);
-            __syncthreads();
-        }
-    } else {
-        dstate_chunk<TI, IT, D>(blockIdx.x, blockIdx.y, s, dout, v, beta, t, Pin, Rin, Sin, SBin, b, dv, gd);
-    }
+                 Bwd b, TI* __restrict__ dv, Gdn2 gd) {
+    dstate_chunk<TI, IT, D>(blockIdx.x, blockIdx.y, s, dout, v, beta, t, Pin, Rin, Sin, SBin, b, dv, gd);
 }
 
 template <typename TI, int D, int GATE>
 __global__ void __launch_bounds__(NTHREADS, 1)
     k_bwd_intra(Shape s, const TI* __restrict__ q, const TI* __restrict__ k,
                 const TI* __restrict__ beta, const float* __restrict__ g, Table t,
-                const int32_t* __restrict__ list, Bwd b, TI* __restrict__ dq, TI* __restrict__ dk,
+                Bwd b, TI* __restrict__ dq, TI* __restrict__ dk,
                 TI* __restrict__ dbeta, float* __restrict__ dg, Gdn2 gd) {
-    if (list) {
-        const int cnt = list[0];
-        for (int w = blockIdx.x; w < cnt; w += gridDim.x) {
-            const int ch = list[1 + w];
-            intra_chunk<TI, D, GATE>(ch / s.H, ch % s.H, s, q, k, beta, g, t, b, dq, dk, dbeta, dg, gd);
-            __syncthreads();
-        }
-    } else {
-        intra_chunk<TI, D, GATE>(blockIdx.x, blockIdx.y, s, q, k, beta, g, t, b, dq, dk, dbeta, dg, gd);
+    intra_chunk<TI, D, GATE>(blockIdx.x, blockIdx.y, s, q, k, beta, g, t, b, dq, dk, dbeta, dg, gd);
+}
+
+// The chunks the tensor-core prep listed as wide (count, then chunk slot * H + head), spread over
+// a grid of one CTA per SM: for each, the state-gradient pass and then the intra pass, which reads
+// what the first wrote for that chunk (made visible within the CTA by the barrier between them).
+template <int GATE>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    k_bwd_wide(Shape s, const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* __restrict__ v,
+               const bf16* __restrict__ beta, const float* __restrict__ g, const bf16* __restrict__ dout, Table t,
+               const bf16* __restrict__ Pin, const bf16* __restrict__ Rin, const bf16* __restrict__ Sin,
+               const bf16* __restrict__ SBin, const int32_t* __restrict__ list, Bwd b, bf16* __restrict__ dq,
+               bf16* __restrict__ dk, bf16* __restrict__ dv, bf16* __restrict__ dbeta, float* __restrict__ dg,
+               Gdn2 gd) {
+    const int cnt = list[0];
+    for (int w = blockIdx.x; w < cnt; w += gridDim.x) {
+        const int ch = list[1 + w];
+        dstate_chunk<bf16, bf16, 128>(ch / s.H, ch % s.H, s, dout, v, beta, t, Pin, Rin, Sin, SBin, b, dv, gd);
+        __syncthreads();
+        intra_chunk<bf16, 128, GATE>(ch / s.H, ch % s.H, s, q, k, beta, g, t, b, dq, dk, dbeta, dg, gd);
+        __syncthreads();
     }
+}
+
+// Shared memory of the two passes (floats): the state-gradient pass's tiles and the intra pass's.
+template <int D>
+constexpr size_t dstate_smem() {
+    constexpr int DC = D > 128 ? 128 : D, LD = DC + 4, LS = SL + 4;
+    return sizeof(float) * (3 * BT * LD + 2 * DC * LS);
+}
+template <int D>
+constexpr size_t intra_smem() {
+    constexpr int DC = D > 128 ? 128 : D, LD = DC + 1, LA = BT + 4;
+    return sizeof(float) * (5 * BT * LD + 2 * BT * LA + 2 * BT + DC);
 }
 
 template <typename TI, typename IT, int D>
 cudaError_t run_dstate(const Shape& s, const void* dout, const void* v, const void* beta, Table t,
-                       const IT* P, const IT* R, const IT* S, const IT* SB, const int32_t* list, Bwd b,
+                       const IT* P, const IT* R, const IT* S, const IT* SB, Bwd b,
                        void* dv, cudaStream_t st, const Gdn2& gd = Gdn2{}) {
-    constexpr int DC = D > 128 ? 128 : D, LD = DC + 4, LS = SL + 4;
-    constexpr size_t smem = sizeof(float) * (3 * BT * LD + 2 * DC * LS);
+    constexpr size_t smem = dstate_smem<D>();
     auto kern = k_bwd_dstate<TI, IT, D>;
     cudaError_t e = set_smem_once<k_bwd_dstate<TI, IT, D>>(smem);
     if (e != cudaSuccess) return e;
-    const dim3 grid = list ? dim3(sm_count()) : dim3(s.NC, s.H);
-    kern<<<grid, NTHREADS, smem, st>>>(s, (const TI*)dout, (const TI*)v, (const TI*)beta, t, P, R, S, SB,
-                                       list, b, (TI*)dv, gd);
+    kern<<<dim3(s.NC, s.H), NTHREADS, smem, st>>>(s, (const TI*)dout, (const TI*)v, (const TI*)beta, t, P, R, S, SB,
+                                                  b, (TI*)dv, gd);
     return cudaGetLastError();
 }
 
 template <typename TI, int D, int GATE>
 cudaError_t run_intra(const Shape& s, const void* q, const void* k, const void* beta, const float* g,
-                      Table t, const int32_t* list, Bwd b, void* dq, void* dk, void* dbeta, float* dg,
+                      Table t, Bwd b, void* dq, void* dk, void* dbeta, float* dg,
                       cudaStream_t st, const Gdn2& gd) {
-    constexpr int DC = D > 128 ? 128 : D, LD = DC + 1, LA = BT + 4;
-    constexpr size_t smem = sizeof(float) * (5 * BT * LD + 2 * BT * LA + 2 * BT + DC);
+    constexpr size_t smem = intra_smem<D>();
     auto kern = k_bwd_intra<TI, D, GATE>;
     cudaError_t e = set_smem_once<k_bwd_intra<TI, D, GATE>>(smem);
     if (e != cudaSuccess) return e;
-    const dim3 grid = list ? dim3(sm_count()) : dim3(s.NC, s.H);
-    kern<<<grid, NTHREADS, smem, st>>>(s, (const TI*)q, (const TI*)k, (const TI*)beta, g, t, list, b,
-                                       (TI*)dq, (TI*)dk, (TI*)dbeta, dg, gd);
+    kern<<<dim3(s.NC, s.H), NTHREADS, smem, st>>>(s, (const TI*)q, (const TI*)k, (const TI*)beta, g, t, b,
+                                                  (TI*)dq, (TI*)dk, (TI*)dbeta, dg, gd);
     return cudaGetLastError();
 }
 
 template <typename TI, int D>
 cudaError_t run_intra_gate(int gate, const Shape& s, const void* q, const void* k, const void* beta,
-                           const float* g, Table t, const int32_t* list, Bwd b, void* dq, void* dk,
+                           const float* g, Table t, Bwd b, void* dq, void* dk,
                            void* dbeta, float* dg, cudaStream_t st, const Gdn2& gd = Gdn2{}) {
     switch (gate) {
-        case 0: return run_intra<TI, D, 0>(s, q, k, beta, g, t, list, b, dq, dk, dbeta, dg, st, gd);
-        case 1: return run_intra<TI, D, 1>(s, q, k, beta, g, t, list, b, dq, dk, dbeta, dg, st, gd);
-        default: return run_intra<TI, D, 2>(s, q, k, beta, g, t, list, b, dq, dk, dbeta, dg, st, gd);
+        case 0: return run_intra<TI, D, 0>(s, q, k, beta, g, t, b, dq, dk, dbeta, dg, st, gd);
+        case 1: return run_intra<TI, D, 1>(s, q, k, beta, g, t, b, dq, dk, dbeta, dg, st, gd);
+        default: return run_intra<TI, D, 2>(s, q, k, beta, g, t, b, dq, dk, dbeta, dg, st, gd);
     }
+}
+
+template <int GATE>
+cudaError_t run_wide(const Shape& s, const void* q, const void* k, const void* v, const void* beta, const float* g,
+                     const void* dout, Table t, FwdTC f, BwdTC bt, Bwd b, void* dq, void* dk, void* dv, void* dbeta,
+                     float* dg, cudaStream_t st, const Gdn2& gd) {
+    constexpr size_t smem = dstate_smem<128>() > intra_smem<128>() ? dstate_smem<128>() : intra_smem<128>();
+    cudaError_t e = set_smem_once<k_bwd_wide<GATE>>(smem);
+    if (e != cudaSuccess) return e;
+    k_bwd_wide<GATE><<<sm_count(), NTHREADS, smem, st>>>(
+        s, (const bf16*)q, (const bf16*)k, (const bf16*)v, (const bf16*)beta, g, (const bf16*)dout, t, bt.P, f.R, f.HS,
+        bt.SBP, f.WLIST, b, (bf16*)dq, (bf16*)dk, (bf16*)dv, (bf16*)dbeta, dg, gd);
+    return cudaGetLastError();
 }
 
 }  // namespace
@@ -618,13 +643,13 @@ cudaError_t run_intra_gate(int gate, const Shape& s, const void* q, const void* 
 cudaError_t launch_bwd_dstate(const Shape& s, int io_bf16, const void* dout, const void* v,
                               const void* beta, Table t, Fwd f, Bwd b, void* dv, cudaStream_t st, const Gdn2& gd) {
     if (s.K == 256)
-        return io_bf16 ? run_dstate<__nv_bfloat16, float, 256>(s, dout, v, beta, t, b.P, f.R, f.SIN, b.SBP, nullptr, b, dv, st, gd)
-                       : run_dstate<float, float, 256>(s, dout, v, beta, t, b.P, f.R, f.SIN, b.SBP, nullptr, b, dv, st, gd);
+        return io_bf16 ? run_dstate<__nv_bfloat16, float, 256>(s, dout, v, beta, t, b.P, f.R, f.SIN, b.SBP, b, dv, st, gd)
+                       : run_dstate<float, float, 256>(s, dout, v, beta, t, b.P, f.R, f.SIN, b.SBP, b, dv, st, gd);
     if (s.K == 128)
-        return io_bf16 ? run_dstate<__nv_bfloat16, float, 128>(s, dout, v, beta, t, b.P, f.R, f.SIN, b.SBP, nullptr, b, dv, st, gd)
-                       : run_dstate<float, float, 128>(s, dout, v, beta, t, b.P, f.R, f.SIN, b.SBP, nullptr, b, dv, st, gd);
-    return io_bf16 ? run_dstate<__nv_bfloat16, float, 64>(s, dout, v, beta, t, b.P, f.R, f.SIN, b.SBP, nullptr, b, dv, st, gd)
-                   : run_dstate<float, float, 64>(s, dout, v, beta, t, b.P, f.R, f.SIN, b.SBP, nullptr, b, dv, st, gd);
+        return io_bf16 ? run_dstate<__nv_bfloat16, float, 128>(s, dout, v, beta, t, b.P, f.R, f.SIN, b.SBP, b, dv, st, gd)
+                       : run_dstate<float, float, 128>(s, dout, v, beta, t, b.P, f.R, f.SIN, b.SBP, b, dv, st, gd);
+    return io_bf16 ? run_dstate<__nv_bfloat16, float, 64>(s, dout, v, beta, t, b.P, f.R, f.SIN, b.SBP, b, dv, st, gd)
+                   : run_dstate<float, float, 64>(s, dout, v, beta, t, b.P, f.R, f.SIN, b.SBP, b, dv, st, gd);
 }
 
 cudaError_t launch_bwd_intra(const Shape& s, int io_bf16, int gate, const void* q, const void* k,
@@ -632,23 +657,24 @@ cudaError_t launch_bwd_intra(const Shape& s, int io_bf16, int gate, const void* 
                              void* dk, void* dbeta, float* dg, cudaStream_t st, const Gdn2& gd) {
     (void)f;
     if (s.K == 256)
-        return io_bf16 ? run_intra_gate<__nv_bfloat16, 256>(gate, s, q, k, beta, g, t, nullptr, b, dq, dk, dbeta, dg, st, gd)
-                       : run_intra_gate<float, 256>(gate, s, q, k, beta, g, t, nullptr, b, dq, dk, dbeta, dg, st, gd);
+        return io_bf16 ? run_intra_gate<__nv_bfloat16, 256>(gate, s, q, k, beta, g, t, b, dq, dk, dbeta, dg, st, gd)
+                       : run_intra_gate<float, 256>(gate, s, q, k, beta, g, t, b, dq, dk, dbeta, dg, st, gd);
     if (s.K == 128)
-        return io_bf16 ? run_intra_gate<__nv_bfloat16, 128>(gate, s, q, k, beta, g, t, nullptr, b, dq, dk, dbeta, dg, st, gd)
-                       : run_intra_gate<float, 128>(gate, s, q, k, beta, g, t, nullptr, b, dq, dk, dbeta, dg, st, gd);
-    return io_bf16 ? run_intra_gate<__nv_bfloat16, 64>(gate, s, q, k, beta, g, t, nullptr, b, dq, dk, dbeta, dg, st, gd)
-                   : run_intra_gate<float, 64>(gate, s, q, k, beta, g, t, nullptr, b, dq, dk, dbeta, dg, st, gd);
+        return io_bf16 ? run_intra_gate<__nv_bfloat16, 128>(gate, s, q, k, beta, g, t, b, dq, dk, dbeta, dg, st, gd)
+                       : run_intra_gate<float, 128>(gate, s, q, k, beta, g, t, b, dq, dk, dbeta, dg, st, gd);
+    return io_bf16 ? run_intra_gate<__nv_bfloat16, 64>(gate, s, q, k, beta, g, t, b, dq, dk, dbeta, dg, st, gd)
+                   : run_intra_gate<float, 64>(gate, s, q, k, beta, g, t, b, dq, dk, dbeta, dg, st, gd);
 }
 
 cudaError_t launch_bwd_wide(const Shape& s, int gate, const void* q, const void* k, const void* v,
                             const void* beta, const float* g, const void* dout, Table t, FwdTC f,
                             BwdTC bt, Bwd scratch, void* dq, void* dk, void* dv, void* dbeta, float* dg,
                             cudaStream_t st, const Gdn2& gd) {
-    cudaError_t e = run_dstate<__nv_bfloat16, __nv_bfloat16, 128>(s, dout, v, beta, t, bt.P, f.R, f.HS, bt.SBP,
-                                                                  f.WLIST, scratch, dv, st, gd);
-    if (e != cudaSuccess) return e;
-    return run_intra_gate<__nv_bfloat16, 128>(gate, s, q, k, beta, g, t, f.WLIST, scratch, dq, dk, dbeta, dg, st, gd);
+    switch (gate) {
+        case 0: return run_wide<0>(s, q, k, v, beta, g, dout, t, f, bt, scratch, dq, dk, dv, dbeta, dg, st, gd);
+        case 1: return run_wide<1>(s, q, k, v, beta, g, dout, t, f, bt, scratch, dq, dk, dv, dbeta, dg, st, gd);
+        default: return run_wide<2>(s, q, k, v, beta, g, dout, t, f, bt, scratch, dq, dk, dv, dbeta, dg, st, gd);
+    }
 }
 
 }  // namespace kda

@@ -19,9 +19,30 @@ __global__ void __launch_bounds__(TBL_THREADS) k_table(Shape s, int B, int T,
     __shared__ int32_t s_cnt[TBL_THREADS];
     __shared__ int32_t s_bad;
     const int tid = threadIdx.x;
+    const int N = s.N;
+    if (!cu) {
+        // equal lengths: every entry by arithmetic, one thread per chunk slot and per sequence
+        // (sequence n owns slots n per .. n per + per - 1; the ranking is the identity)
+        const int per = (T + BT - 1) / BT;
+        for (int slot = tid; slot < s.NC; slot += TBL_THREADS) {
+            const int n = slot / per, j = slot - n * per;
+            t.chunk_tok0[slot] = n * T + j * BT;
+            t.chunk_len[slot] = min(BT, T - j * BT);
+        }
+        for (int n = tid; n < N; n += TBL_THREADS) {
+            t.seq_tok0[n] = n * T;
+            t.seq_len[n] = T;
+            t.seq_chunk0[n] = n * per;
+            t.seq_order[n] = n;
+        }
+        if (tid == 0) {
+            t.seq_chunk0[N] = N * per;
+            t.err[0] = 0;
+        }
+        return;
+    }
     if (tid == 0) s_bad = 0;
     __syncthreads();
-    const int N = s.N;
     const int per = (N + TBL_THREADS - 1) / TBL_THREADS;
     const int n0 = min(N, tid * per), n1 = min(N, n0 + per);
     // clamped bounds of this thread's sequences; count their chunks
