@@ -658,8 +658,7 @@ static kda_status chunk_fwd_core(const kda_problem* p, void* o, float* ht, void*
     Carver cw{static_cast<char*>(ws)};
     kda::Table t = carve_table(cw, d);
     const int bf16 = p->io == KDA_BF16;
-    cudaError_t e = traced("k_table", cs, [&] { return kda::launch_table(s, p->B, p->T, p->cu_seqlens, t, cs); });
-    if (e != cudaSuccess) return cuda_fail(e, "chunk table");
+    cudaError_t e;
     if (use_tc(p)) {
         kda::FwdTC f;
         const bool save = p->save_policy != 0;
@@ -669,6 +668,11 @@ static kda_status chunk_fwd_core(const kda_problem* p, void* o, float* ht, void*
         } else {
             carve_fwd_tc(cw, d, f, false);
         }
+        kda::TableZeros z;   // the prep's list of wide chunks starts empty
+        z.p[0] = f.WLIST;
+        z.n[0] = 1;
+        e = traced("k_table", cs, [&] { return kda::launch_table(s, p->B, p->T, p->cu_seqlens, t, cs, z); });
+        if (e != cudaSuccess) return cuda_fail(e, "chunk table");
         e = traced("k_prep_tc", cs, [&] { return kda::launch_prep_tc(s, (int)p->gate, save ? 1 : 0, p->q, p->k, p->v, p->beta, p->g, t, f, cs, kda::Gdn2{p->erase, p->write}); });
         if (e != cudaSuccess) return cuda_fail(e, "prep");
         e = traced("k_prep_wide", cs, [&] { return kda::launch_prep_wide(s, (int)p->gate, p->q, p->k, p->v, p->beta, p->g, t, f, cs, kda::Gdn2{p->erase, p->write}); });
@@ -686,6 +690,8 @@ static kda_status chunk_fwd_core(const kda_problem* p, void* o, float* ht, void*
         if (sd && (e = side_join(sd, cs)) != cudaSuccess) return cuda_fail(e, "side stream");
         return KDA_OK;
     }
+    e = traced("k_table", cs, [&] { return kda::launch_table(s, p->B, p->T, p->cu_seqlens, t, cs); });
+    if (e != cudaSuccess) return cuda_fail(e, "chunk table");
     kda::Fwd f;
     if (p->save_policy) {
         Carver cs2{static_cast<char*>(saved)};
@@ -753,7 +759,21 @@ static kda_status chunk_bwd_core(const kda_problem* p, const void* dout, const f
         kda::Bwd scr;
         carve_bwd_tc(cw, d, b, scr);
         const int gate = (int)p->gate;
-        cudaError_t e = traced("k_table", cs, [&] { return kda::launch_table(s, p->B, p->T, p->cu_seqlens, t, cs); });
+        // zeroed by the table's launch: the recompute prep's list of wide chunks and, for equal
+        // lengths, the claim counters and ready flags after the two state adjoints of the piece area
+        kda::TableZeros z;
+        if (!save) {
+            z.p[0] = f.WLIST;
+            z.n[0] = 1;
+        }
+        if (d.per) {
+            char* pz = cw.p + 2 * up(state_bytes(d));
+            z.p[1] = reinterpret_cast<int32_t*>(pz);
+            z.n[1] = kda::MAX_PIECES;
+            z.p[2] = reinterpret_cast<int32_t*>(pz + up(4 * kda::MAX_PIECES));
+            z.n[2] = d.NC * d.H;
+        }
+        cudaError_t e = traced("k_table", cs, [&] { return kda::launch_table(s, p->B, p->T, p->cu_seqlens, t, cs, z); });
         if (e != cudaSuccess) return cuda_fail(e, "chunk table");
         Side* sd = nullptr;
         if (!save) {
@@ -773,14 +793,11 @@ static kda_status chunk_bwd_core(const kda_problem* p, const void* dout, const f
         }
         if (bwd_joint(p, d)) {
             // the joint schedule: scans and consumer in one cooperative launch; the ready flags and the
-            // unit counter start at zero
+            // unit counter start at zero (the table's launch zeroed them)
             cw.take<float>(state_bytes(d));
             cw.take<float>(state_bytes(d));
             int* ctr = cw.take<int>(4 * kda::MAX_PIECES);
             int* flags = cw.take<int>(sizeof(int) * (size_t)d.NC * d.H);
-            if ((e = cudaMemsetAsync(ctr, 0, 4 * kda::MAX_PIECES, cs)) != cudaSuccess ||
-                (e = cudaMemsetAsync(flags, 0, sizeof(int) * (size_t)d.NC * d.H, cs)) != cudaSuccess)
-                return cuda_fail(e, "joint schedule flags");
             kda::ConsPiece pc;
             pc.per = d.per;
             pc.ctr = ctr;
@@ -808,8 +825,7 @@ static kda_status chunk_bwd_core(const kda_problem* p, const void* dout, const f
             // stream, which also holds the recompute scan under policy R); the state adjoint entering a
             // piece goes to the next through one of two fp32 buffers
             float* hb[2] = {cw.take<float>(state_bytes(d)), cw.take<float>(state_bytes(d))};
-            int* ctr = cw.take<int>(4 * kda::MAX_PIECES);
-            if ((e = cudaMemsetAsync(ctr, 0, 4 * kda::MAX_PIECES, cs)) != cudaSuccess) return cuda_fail(e, "claim counters");
+            int* ctr = cw.take<int>(4 * kda::MAX_PIECES);   // zeroed by the table's launch
             for (int q = 0; q < P; ++q) {
                 kda::ConsPiece pc;
                 pc.per = d.per;

@@ -338,7 +338,14 @@ void set_last_error(const char* msg);
 // Each returns cudaSuccess or the launch error. Defined in the .cu files.
 // Self-test of the device-timeout path (sets bit 1 of t.err after a bounded wait of limit_ns).
 cudaError_t launch_wait_selftest(Table t, uint64_t limit_ns, cudaStream_t st);
-cudaError_t launch_table(const Shape& s, int B, int T, const int32_t* cu, Table t, cudaStream_t st);
+// Counters the chunk table's launch zeroes as well (the list of wide chunks, the backward's claim
+// counters and ready flags), so that they need no launches of their own.
+struct TableZeros {
+    int32_t* p[3] = {nullptr, nullptr, nullptr};
+    int n[3] = {0, 0, 0};
+};
+cudaError_t launch_table(const Shape& s, int B, int T, const int32_t* cu, Table t, cudaStream_t st,
+                         const TableZeros& z = TableZeros{});
 // GatedDeltaNet-2 ("GatedDeltaNet-2 (NVlabs) — official spec transcription", §3):
 // an erase vector b per key channel and a write vector w per value channel take
 // beta's place (E = b .* K exp(G), Z = w .* V); erase NULL: the beta rule. Every
@@ -404,7 +411,8 @@ cudaError_t launch_prep(const Shape& s, int io_bf16, int gate, const void* q, co
 cudaError_t launch_fwd_scan(const Shape& s, int io_bf16, int mode, const float* h0, Table t,
                             Fwd f, void* o, float* ht, cudaStream_t st);
 
-// Tensor-core path (bf16 I/O, K = V = 128).
+// Tensor-core path (bf16 I/O, K = V = 128). The prep appends to the list of wide chunks, whose
+// count the caller zeroes first (the chunk table's launch does).
 cudaError_t launch_prep_tc(const Shape& s, int gate, int for_bwd, const void* q, const void* k,
                            const void* v, const void* beta, const float* g, Table t, FwdTC f,
                            cudaStream_t st, const Gdn2& gd = Gdn2{});

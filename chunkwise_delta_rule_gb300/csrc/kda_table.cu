@@ -15,11 +15,14 @@ namespace {
 constexpr int TBL_THREADS = 1024;
 
 __global__ void __launch_bounds__(TBL_THREADS) k_table(Shape s, int B, int T,
-                                                       const int32_t* __restrict__ cu, Table t) {
+                                                       const int32_t* __restrict__ cu, Table t, TableZeros z) {
     __shared__ int32_t s_cnt[TBL_THREADS];
     __shared__ int32_t s_bad;
     const int tid = threadIdx.x;
     const int N = s.N;
+#pragma unroll
+    for (int i = 0; i < 3; ++i)
+        for (int j = tid; j < z.n[i]; j += TBL_THREADS) z.p[i][j] = 0;
     if (!cu) {
         // equal lengths: every entry by arithmetic, one thread per chunk slot and per sequence
         // (sequence n owns slots n per .. n per + per - 1; the ranking is the identity)
@@ -139,8 +142,9 @@ cudaError_t launch_wait_selftest(Table t, uint64_t limit_ns, cudaStream_t st) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_table(const Shape& s, int B, int T, const int32_t* cu, Table t, cudaStream_t st) {
-    k_table<<<1, TBL_THREADS, 0, st>>>(s, B, T, cu, t);
+cudaError_t launch_table(const Shape& s, int B, int T, const int32_t* cu, Table t, cudaStream_t st,
+                         const TableZeros& z) {
+    k_table<<<1, TBL_THREADS, 0, st>>>(s, B, T, cu, t, z);
     return cudaGetLastError();
 }
 

@@ -966,8 +966,6 @@ cudaError_t run_prep(const Shape& s, const void* q, const void* k, const void* v
                      const float* g, Table t, FwdTC f, cudaStream_t st, const Gdn2& gd) {
     cudaError_t e = set_smem_once<k_prep_tc<GATE, BWD, GD2>>(PREP_SMEM);
     if (e != cudaSuccess) return e;
-    e = cudaMemsetAsync(f.WLIST, 0, sizeof(int32_t), st);   // the list of wide chunks starts empty
-    if (e != cudaSuccess) return e;
     CUtensorMap mq, mk, mv, mg;
     memset(&mg, 0, sizeof(mg));
     // the inputs at their own widths K, V (<= D): the boxes' columns past them read as zeros
