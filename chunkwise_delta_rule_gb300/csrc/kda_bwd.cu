@@ -58,7 +58,8 @@ __device__ __forceinline__ void dstate_chunk(int c, int h, const Shape& s, const
     if (len <= 0) return;
     const int tok0 = t.chunk_tok0[c];
     const int H = s.H;
-    const int Vw = s.V;   // token rows of dO, v, write and of dv, dwrite (V = D but for the wide chunks
+    constexpr bool TCW = D == 128;   // the tensor-core path's wide chunks (narrower rows, grouped heads)
+    const int Vw = TCW ? s.V : D;   // token rows of dO, v, write and of dv, dwrite (V = D but for the wide chunks
                           // of the tensor-core path, whose rows may be narrower)
     const size_t ch = (size_t)c * H + h;
     const int lane = tid & 31, warp = tid >> 5;
@@ -102,7 +103,7 @@ __device__ __forceinline__ void dstate_chunk(int c, int h, const Shape& s, const
                 const int r = warp + i * (NTHREADS / 32);
                 if (r < len) {
                     const size_t tok = (size_t)(tok0 + r) * H + h;
-                    const float bt = wr ? 0.f : ld(beta + (size_t)(tok0 + r) * heads_g(s) + h / s.Gg);
+                    const float bt = wr ? 0.f : ld(beta + (size_t)(tok0 + r) * (TCW ? heads_g(s) : H) + (TCW ? h / s.Gg : h));
                     for (int cc = lane; cc < DC; cc += 32) {
                         const int col = v0 + cc;
                         if (col >= Vw) break;
@@ -223,7 +224,8 @@ __device__ __forceinline__ void intra_chunk(int c, int h, const Shape& s, const 
     if (len <= 0) return;
     const int tok0 = t.chunk_tok0[c];
     const int H = s.H;
-    const int Kw = s.K;   // token rows of q, k, g, erase and of dq, dk, dg, derase (K = D but for the
+    constexpr bool TCW = D == 128;   // the tensor-core path's wide chunks (narrower rows, grouped heads)
+    const int Kw = TCW ? s.K : D;   // token rows of q, k, g, erase and of dq, dk, dg, derase (K = D but for the
                           // wide chunks of the tensor-core path, whose rows may be narrower)
     const size_t ch = (size_t)c * H + h;
     const float scale = s.scale;
@@ -238,7 +240,7 @@ __device__ __forceinline__ void intra_chunk(int c, int h, const Shape& s, const 
                           [&](int r, int cc, float x) { sHQ[r * LA + cc] = x; });
     }
     // heads of q, k and of g, beta, erase (value head h reads q, k of head h / Gq, the rest of h / Gg)
-    const int hq = h / s.Gq, Hq = heads_q(s), hg = h / s.Gg, Hg = heads_g(s);
+    const int hq = TCW ? h / s.Gq : h, Hq = TCW ? heads_q(s) : H, hg = TCW ? h / s.Gg : h, Hg = TCW ? heads_g(s) : H;
     if (tid < BT) sBeta[tid] = (tid < len && !gd.erase) ? ldg(beta + (size_t)(tok0 + tid) * Hg + hg) : 0.f;
     // GatedDeltaNet-2: the erase vector takes beta's place on the key side (E = b .* K exp(G))
     const TI* er = static_cast<const TI*>(gd.erase);

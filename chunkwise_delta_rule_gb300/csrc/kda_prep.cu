@@ -49,7 +49,10 @@ __device__ __forceinline__ void prep_chunk(int c, int h, const Shape& s, const T
     if (n <= 0) return;
     const int tok0 = t.chunk_tok0[c];
     const int H = s.H;
-    const int hq = h / s.Gq, Hq = heads_q(s), hg = h / s.Gg, Hg = heads_g(s);   // heads of q, k and of g, beta, erase
+    // heads of q, k and of g, beta, erase: grouped or per block only for the wide chunks of the
+    // tensor-core path (D = 128); the CUDA-core path's inputs have one head per value head
+    constexpr bool TCW = D == 128;
+    const int hq = TCW ? h / s.Gq : h, Hq = TCW ? heads_q(s) : H, hg = TCW ? h / s.Gg : h, Hg = TCW ? heads_g(s) : H;
     const size_t ch = (size_t)c * H + h;
 
     if (tid < BT) sBeta[tid] = (tid < n && !gd.erase) ? ldg(beta + (size_t)(tok0 + tid) * Hg + hg) : 0.f;
@@ -57,7 +60,7 @@ __device__ __forceinline__ void prep_chunk(int c, int h, const Shape& s, const T
     // q, k, g and erase are K wide, those of v and write V wide (K = V = D but for the wide chunks
     // of the tensor-core path, whose inputs may be narrower than its 128 columns); columns past
     // them read as zeros.
-    const int Kw = s.K, Vw = s.V;
+    const int Kw = TCW ? s.K : D, Vw = TCW ? s.V : D;
     const TI* er = static_cast<const TI*>(gd.erase);
     auto ebeta = [&](int r, int gcol) {
         return er ? ((r < n && gcol < Kw) ? ld(er + ((size_t)(tok0 + r) * Hg + hg) * Kw + gcol) : 0.f) : sBeta[r];
