@@ -20,7 +20,8 @@
 //     [T_q ; T_e] = [H_q ; D] (K zeta)        (A operand read from TMEM)
 //     T_y^T       = [E_alpha^T | Q_alpha^T] [D ; H_q]
 // with alpha = 2^(G2 - c), zeta = 2^(c - G2) around the per-feature midpoint
-// c ("Matrix intra for vector-gated interactions", centered factors); a scalar
+// c ("Matrix intra for vector-gated interactions", centered factors), alpha and
+// 2^c as the forward prep saved them for this pass; a scalar
 // gate instead folds 2^(G2_i - G2_j) into H_q and D and uses unit factors, so
 // the key-gradient contractions carry the gate reduction without a key Gram
 // matrix ("Gram elimination for scalar-gate gradients"). Then the chain rule
@@ -409,7 +410,8 @@ __global__ void __launch_bounds__(ST_ALL, 1)
 // loaded while this one finishes (three groups, each on its own mbarrier):
 //   X1: [R ; S], S+bar tile images        } after this unit's phase-B MMAs (the phase-B
 //   X2: [dO ; P], v                        }   operands are the last readers of the X region)
-//   C:  k, q (SW128 rows), g (fp32 rows)  after this unit's key-major epilogue
+//   C:  k, q (SW128 rows), the prep's   after this unit's key-major epilogue
+//       alpha (per-channel gate: fp32 token rows; scalar gate: one per token)
 // Every accumulator the chain rule reads is key-major (TMEM lane = key k, column = token j), so
 // one pass in registers forms dq, dk, dbeta and G_bar, the reverse in-chunk cumsum runs inside
 // each thread over its tokens, and dq, dk, dg go from registers to HBM.
@@ -426,8 +428,8 @@ constexpr int X_BT = 98304;      // [D ; H_q]       tf32 [128][64]   32 KB   (ro
 constexpr int X_END = 131072;
 constexpr int X_STG = X_END;     // per-warp staging of the transposed bf16 stores, 16 x 512 B; from the
                                  // next unit's group C to its alpha pass, a scalar gate's alphas
-constexpr int C_A = X_STG + 16 * 512;             // g (dense rows, as TMA lands them), then alpha
-                                                  // = 2^(G2 - c) at aidx(row, col), fp32 [64][128]
+constexpr int C_A = X_STG + 16 * 512;             // the prep's alpha = 2^(G2 - c) as fp32 token rows
+                                                  // [64][128] (per-channel gate), then key-major
 constexpr int C_K = C_A + 4 * BT * D;             // k bf16 [64][128], SW128 rows
 constexpr int C_Q = C_K + 2 * BT * D;             // q bf16 [64][128], SW128 rows
 constexpr int C_MISC = C_Q + 2 * BT * D;          // small arrays (floats)
@@ -456,8 +458,8 @@ __device__ __forceinline__ uint32_t swrow(uint32_t kcol, int kch, int j) {
     return kcol + (uint32_t)(j * 128) + ((uint32_t)(kch ^ (j & 7)) << 4);
 }
 
-// Key-major tiles the cumsum writes over the tiles it has read (each thread writes, and later
-// reads, its own key and 16 tokens): alpha fp32 [128 keys][64 tokens] over the g tile, k and q
+// Key-major tiles the alpha pass writes over the tiles it has read (each thread writes, and later
+// reads, its own key and 16 tokens): alpha fp32 [128 keys][64 tokens] over the alpha rows, k and q
 // bf16 [128 keys][64 tokens] over the token-major k and q tiles. Their 16-byte chunks are XORed
 // with the key, so that eight consecutive keys reach distinct bank groups.
 __device__ __forceinline__ int akm4(int kr, int c4) { return kr * BT + ((c4 ^ (kr & 15)) << 2); }   // alpha, tokens 4 c4 ..
@@ -607,7 +609,7 @@ __device__ __forceinline__ void cons_body(const Shape& s, const CUtensorMap* tmq
     float* sA = reinterpret_cast<float*>(base + C_A);
     const unsigned char* sK = base + C_K;
     const unsigned char* sQ = base + C_Q;
-    bf16* sKm = reinterpret_cast<bf16*>(base + C_K);   // the same tiles, key-major after the cumsum
+    bf16* sKm = reinterpret_cast<bf16*>(base + C_K);   // the same tiles, key-major after the alpha pass
     bf16* sQm = reinterpret_cast<bf16*>(base + C_Q);
     float* sm = reinterpret_cast<float*>(base + C_MISC);
     float* sBeta = sm + M_BETA;
@@ -701,7 +703,7 @@ __device__ __forceinline__ void cons_body(const Shape& s, const CUtensorMap* tmq
         if (warp == 0) {
             tc::fence_after_sync();
             // phase A (warp-uniform descriptors, one elected lane issuing); it needs only the X
-            // tiles, so it runs under the rowsum, dv and cumsum passes:
+            // tiles, so it runs under the rowsum, dv and alpha passes:
             //   [dO ; P] R^T -> [H_q ; -D] (token rows), S [dO ; P]^T -> [S dO^T | S P^T] and
             //   S+bar R^T -> F_bar^T (key rows); S is rows 64..191 of the [R ; S] tile
             const uint32_t i64 = tc::idesc_bf16(128, 64), i128 = tc::idesc_bf16(128, 128);
