@@ -193,7 +193,7 @@ class ClockSampler:
         try:
             os.makedirs(os.path.dirname(os.path.abspath(self.path)), exist_ok=True)
             cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
-                   "-lms", "200"]
+                   "-lms", "50"]
             if self.uuid:
                 cmd += ["--id=" + self.uuid]
             self.fh = open(self.path, "w")
