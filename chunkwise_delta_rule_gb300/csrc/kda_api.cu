@@ -977,6 +977,8 @@ static kda_status chunk_bwd_pro(const kda_problem* p, const void* dout, const fl
     a.dA_log = dA_log;
     const kda::Shape s = shape_of(p, d);
     cudaError_t e = traced("k_epilogue", cs, [&] { return kda::launch_epilogue(s, p->io == KDA_BF16, (int)p->gate, a, cs); });
+    if (e == cudaSuccess && p->A_log)
+        e = traced("k_prologue_sum", cs, [&] { return kda::launch_prologue_sum(s, (int)p->gate, a, cs); });
     return e == cudaSuccess ? KDA_OK : cuda_fail(e, "epilogue");
 }
 

@@ -379,6 +379,8 @@ struct EpilogueArgs {
 int prologue_blocks(int Ttot);
 cudaError_t launch_prologue(const Shape& s, int bf16, int gate, const PrologueArgs& a, cudaStream_t st);
 cudaError_t launch_epilogue(const Shape& s, int bf16, int gate, const EpilogueArgs& a, cudaStream_t st);
+// dt_bias's and A_log's gradients from the epilogue's token-block partial sums (no-op without A_log).
+cudaError_t launch_prologue_sum(const Shape& s, int gate, const EpilogueArgs& a, cudaStream_t st);
 // unequal or narrower widths (kda_pad.cu): [M][R][C] <-> [M][Rd][Cd], zero fill (es = element bytes)
 cudaError_t launch_pad(bool pad, int es, long long M, int R, int C, int Rd, int Cd, const void* src, void* dst,
                        cudaStream_t st);

@@ -318,7 +318,11 @@ cudaError_t launch_epilogue(const Shape& s, int bf16, int gate, const EpilogueAr
         case 256: e = bf16 ? run_epilogue_k<__nv_bfloat16, 256>(s, gate, a, st) : run_epilogue_k<float, 256>(s, gate, a, st); break;
         default: return cudaErrorInvalidValue;
     }
-    if (e != cudaSuccess || gate == 0 || !a.A_log) return e;
+    return e;
+}
+
+cudaError_t launch_prologue_sum(const Shape& s, int gate, const EpilogueArgs& a, cudaStream_t st) {
+    if (gate == 0 || !a.A_log) return cudaSuccess;
     const int NC = gate == 2 ? s.K : 1;
     const int n = s.H * NC;
     k_prologue_sum<<<(n + 255) / 256, 256, 0, st>>>(prologue_blocks(s.Ttot), s.H, NC, a.pz, a.pA, a.ddt_bias,
