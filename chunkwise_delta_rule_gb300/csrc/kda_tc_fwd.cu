@@ -225,11 +225,19 @@ __global__ void __launch_bounds__(PT, 2)
         if ((tid & 1) * 64 < w) tc::prefetch_l2(vec + row * w + (tid & 1) * 64);
     }
     if (GATE != 2) {
-        // scalar gate: the G tile repeats the token's log-decay; no gate: zeros
-        for (int idx = tid; idx < BT * D / 4; idx += PT) {
-            const int r = idx >> 5, c4 = (idx & 31) * 4;
-            const float x = (GATE == 1 && r < n) ? __ldg(g + (size_t)(tok0 + r) * Hg + hg) : 0.f;
-            *reinterpret_cast<float4*>(sA + r * LG + c4) = make_float4(x, x, x, x);
+        // scalar gate: the G tile repeats the token's log-decay; no gate: zeros (this thread's eight
+        // rows loaded before any of its stores)
+        constexpr int NF = BT * D / 4 / PT;
+        float xr[NF];
+#pragma unroll
+        for (int u = 0; u < NF; ++u) {
+            const int r = (tid + PT * u) >> 5;
+            xr[u] = (GATE == 1 && r < n) ? __ldg(g + (size_t)(tok0 + r) * Hg + hg) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < NF; ++u) {
+            const int idx = tid + PT * u, r = idx >> 5, c4 = (idx & 31) * 4;
+            *reinterpret_cast<float4*>(sA + r * LG + c4) = make_float4(xr[u], xr[u], xr[u], xr[u]);
         }
     }
     if (warp == 0) {
