@@ -37,6 +37,9 @@ __host__ __device__ __forceinline__ int tile_el(int R, int r, int col) {
 // encoded.
 bool tmap_rows_bf16(CUtensorMap* m, const void* base, int Ttot, int H, int D);
 bool tmap_rows_f32(CUtensorMap* m, const void* base, int Ttot, int H, int D, int box_x = 0);
+// fp32 states [NH][K][V] in boxes of 32 keys x 32 value columns, 128-byte swizzled (K, V multiples of
+// 32; false when the base is not 16-byte aligned).
+bool tmap_state_f32(CUtensorMap* m, const float* base, int NH, int K, int V);
 
 // Chunk bookkeeping built on the device from cu_seqlens (or from B, T).
 struct Table {

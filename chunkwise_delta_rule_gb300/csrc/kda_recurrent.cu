@@ -14,7 +14,10 @@
 // the decay -exp(A_log) softplus(g + dt_bias) or lower_bound sigmoid(exp(A_log)
 // (g + dt_bias)). GatedDeltaNet-2 (same page, §3) erases along b .* k and writes
 // w .* v: r_t = w_t .* v_t - S~^T (b_t .* k_t).
+#include <string.h>
+
 #include "kda_internal.cuh"
+#include "tc.cuh"
 
 namespace kda {
 namespace {
@@ -148,9 +151,22 @@ struct Tok {
     }
 };
 
+// The state slice moves by TMA when its tensor map could be made (tma bit 0: h0, bit 1: ht): one box
+// of 32 keys x 32 columns per 32 keys into a 128-byte-swizzled tile, from which each lane takes its
+// key row's two 16-byte chunks (chunk c of row r at c ^ (r mod 8): the eight lanes of a quarter warp
+// reach distinct banks); otherwise each lane reads and writes its 32 bytes per key directly.
+__device__ __forceinline__ unsigned char* rec_chunk(unsigned char* tile, int j, int lane, int c) {
+    return tile + j * 4096 + lane * 128 + ((c ^ (lane & 7)) << 4);
+}
+
 template <typename TI, int K, int GATE>
-__global__ void __launch_bounds__(RT) k_recurrent(Shape s, RecIO io) {
+__global__ void __launch_bounds__(RT, K <= 128 ? 6 : 1) k_recurrent(Shape s, RecIO io, const __grid_constant__ CUtensorMap tmh0,
+                                                  const __grid_constant__ CUtensorMap tmht, int tma) {
     constexpr int KJ = K / 32;
+    extern __shared__ unsigned char rsm_raw[];
+    unsigned char* tile = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(rsm_raw) + 1023) &
+                                                           ~static_cast<uintptr_t>(1023));
+    uint64_t* bar = reinterpret_cast<uint64_t*>(tile + K * 128);
     const int VB = s.V / RV;
     const int n = blockIdx.x / VB, vb = blockIdx.x - n * VB, h = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -172,6 +188,30 @@ __global__ void __launch_bounds__(RT) k_recurrent(Shape s, RecIO io) {
     // the state slice: keys lane + 32 j, columns col0 .. col0 + 7
     float S[KJ][8];
     const size_t sb = ((size_t)n * H + h) * K * V;
+    if ((tma & 1) && io.h0) {
+        if (threadIdx.x == 0) {
+            tc::mbar_init(bar, 1);
+            tc::fence_mbar_init();
+            tc::mbar_arrive_expect_tx(bar, K * 128);
+#pragma unroll
+            for (int j = 0; j < KJ; ++j) tc::tma_load3(tc::smem_u32(tile + j * 4096), &tmh0, vb * RV, 32 * j, n * H + h, bar);
+        }
+        __syncthreads();
+        if (!__syncthreads_and(tc::mbar_wait(bar, 0))) {   // a lost copy: recorded, and it lands first
+            if (threadIdx.x == 0) {
+                if (io.err) atomicOr(io.err, 2);
+                tc::mbar_wait(bar, 0);
+            }
+            return;
+        }
+#pragma unroll
+        for (int j = 0; j < KJ; ++j) {
+            const float4 x0 = *reinterpret_cast<const float4*>(rec_chunk(tile, j, lane, 2 * warp));
+            const float4 x1 = *reinterpret_cast<const float4*>(rec_chunk(tile, j, lane, 2 * warp + 1));
+            S[j][0] = x0.x; S[j][1] = x0.y; S[j][2] = x0.z; S[j][3] = x0.w;
+            S[j][4] = x1.x; S[j][5] = x1.y; S[j][6] = x1.z; S[j][7] = x1.w;
+        }
+    } else {
 #pragma unroll
     for (int j = 0; j < KJ; ++j) {
         if (io.h0) {
@@ -183,6 +223,7 @@ __global__ void __launch_bounds__(RT) k_recurrent(Shape s, RecIO io) {
 #pragma unroll
             for (int c = 0; c < 8; ++c) S[j][c] = 0.f;
         }
+    }
     }
     Tok<TI, KJ, GATE> cur, nxt;
     const int Hk = H / io.G, hk = h / io.G;   // key heads; this value head's key head
@@ -222,7 +263,24 @@ __global__ void __launch_bounds__(RT) k_recurrent(Shape s, RecIO io) {
         if ((lane & 3) == 0) st(static_cast<TI*>(io.o) + ((size_t)t * H + h) * V + cme, ov);
         cur = nxt;
     }
-    if (io.ht) {
+    if (io.ht && (tma & 2)) {
+        // the slice into the tile (the loads, if any, were all read before the token loop), then one
+        // TMA store per 32 keys; the tile must outlive the stores' reads
+        __syncthreads();
+#pragma unroll
+        for (int j = 0; j < KJ; ++j) {
+            *reinterpret_cast<float4*>(rec_chunk(tile, j, lane, 2 * warp)) = make_float4(S[j][0], S[j][1], S[j][2], S[j][3]);
+            *reinterpret_cast<float4*>(rec_chunk(tile, j, lane, 2 * warp + 1)) = make_float4(S[j][4], S[j][5], S[j][6], S[j][7]);
+        }
+        tc::fence_async_smem();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+#pragma unroll
+            for (int j = 0; j < KJ; ++j) tc::tma_store3(&tmht, vb * RV, 32 * j, n * H + h, tc::smem_u32(tile + j * 4096));
+            tc::bulk_commit();
+            tc::bulk_wait_all();
+        }
+    } else if (io.ht) {
 #pragma unroll
         for (int j = 0; j < KJ; ++j) {
             float4* dst = reinterpret_cast<float4*>(io.ht + sb + (size_t)(lane + 32 * j) * V + col0);
@@ -238,10 +296,21 @@ cudaError_t run_recurrent_k(const Shape& s, int gate, const RecIO& io, cudaStrea
     if (blocks <= 0) return cudaSuccess;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
     const dim3 grid((unsigned)blocks, s.H);
+    // the states by TMA where their maps can be made (16-byte aligned; K and V are multiples of 32)
+    CUtensorMap mh0, mht;
+    memset(&mh0, 0, sizeof(mh0));
+    memset(&mht, 0, sizeof(mht));
+    const long long nh = (long long)s.N * s.H;
+    int tma = 0;
+    if (nh <= 0x7fffffffLL) {
+        if (io.h0 && tmap_state_f32(&mh0, io.h0, (int)nh, K, s.V)) tma |= 1;
+        if (io.ht && tmap_state_f32(&mht, io.ht, (int)nh, K, s.V)) tma |= 2;
+    }
+    const size_t smem = tma ? (size_t)K * 128 + 1024 + 16 : 0;
     switch (gate) {
-        case 0: k_recurrent<TI, K, 0><<<grid, RT, 0, st>>>(s, io); break;
-        case 1: k_recurrent<TI, K, 1><<<grid, RT, 0, st>>>(s, io); break;
-        default: k_recurrent<TI, K, 2><<<grid, RT, 0, st>>>(s, io); break;
+        case 0: k_recurrent<TI, K, 0><<<grid, RT, smem, st>>>(s, io, mh0, mht, tma); break;
+        case 1: k_recurrent<TI, K, 1><<<grid, RT, smem, st>>>(s, io, mh0, mht, tma); break;
+        default: k_recurrent<TI, K, 2><<<grid, RT, smem, st>>>(s, io, mh0, mht, tma); break;
     }
     return cudaGetLastError();
 }
