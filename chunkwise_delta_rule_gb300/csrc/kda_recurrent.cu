@@ -185,6 +185,10 @@ __global__ void __launch_bounds__(RT, K <= 128 ? 6 : 1) k_recurrent(Shape s, Rec
         t0 = n * io.T;
         t1 = t0 + io.T;
     }
+    // the first token's inputs, in flight while the state slice loads
+    Tok<TI, KJ, GATE> cur, nxt;
+    const int Hk = H / io.G, hk = h / io.G;   // key heads; this value head's key head
+    if (t0 < t1) cur.load(io, (size_t)t0 * H + h, (size_t)t0 * Hk + hk, K, V, cme, lane);
     // the state slice: keys lane + 32 j, columns col0 .. col0 + 7
     float S[KJ][8];
     const size_t sb = ((size_t)n * H + h) * K * V;
@@ -225,9 +229,6 @@ __global__ void __launch_bounds__(RT, K <= 128 ? 6 : 1) k_recurrent(Shape s, Rec
         }
     }
     }
-    Tok<TI, KJ, GATE> cur, nxt;
-    const int Hk = H / io.G, hk = h / io.G;   // key heads; this value head's key head
-    if (t0 < t1) cur.load(io, (size_t)t0 * H + h, (size_t)t0 * Hk + hk, K, V, cme, lane);
     for (int t = t0; t < t1; ++t) {
         if (t + 1 < t1) nxt.load(io, (size_t)(t + 1) * H + h, (size_t)(t + 1) * Hk + hk, K, V, cme, lane);
         cur.finish(io, h, K, lane, s.scale);
