@@ -312,3 +312,25 @@ def _set(p, **kw):
     for k, v in kw.items():
         setattr(p, k, v)
     return p
+
+
+def test_in_place_grouped_reads_follow_the_tensor_core_path():
+    """Grouped heads and value blocks read q, k (and g, beta) in place exactly when the problem runs on
+    the tensor-core path at its own widths without the prologue; the workspace shows which."""
+    def up(x):
+        return (x + 255) // 256 * 256
+
+    T = 2 * 130
+    # bf16 80/112 with two value heads per key head: in place (no q, k copies in the forward)
+    g, flat = _set(_prob(H=2, K=80, V=112), HV=4), _prob(H=4, K=80, V=112)
+    assert _ws(g, 0) == _ws(flat, 0)
+    # fp32 I/O at 64: the CUDA-core path, q and k copied per value head
+    g, flat = _set(_prob(H=2, K=64, V=64, io=1), HV=4), _prob(H=4, K=64, V=64, io=1)
+    assert _ws(g, 0) == _ws(flat, 0) + 2 * up(4 * T * 4 * 64)
+    # bf16 96/160: two 80-wide value blocks, native widths, in place (the blocks' final states only)
+    p, inner = _prob(K=96, V=160), _set(_prob(K=96, V=80), HV=6)
+    assert _ws(p, 0) == _ws(inner, 0) + up(4 * 2 * 3 * 96 * 160)
+    # bf16 128/200: two blocks of 100, padded to 128 inside, so beta and g repeat per block and the
+    # value rows are padded to 200 (no copy: NB * Vb = V)
+    p, inner = _prob(V=200), _set(_prob(V=100), HV=6)
+    assert _ws(p, 0) == _ws(inner, 0) + up(2 * T * 3 * 2) + up(4 * T * 3 * 2 * 128) + up(4 * 2 * 3 * 128 * 200)
