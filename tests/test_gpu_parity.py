@@ -281,8 +281,9 @@ def _sample_pairs(case, idx):
     return out
 
 
-# The benchmark times the save policy with the library's default backward schedule (time pieces for
-# equal-length batches whose reverse scan leaves SMs idle); the recompute policy runs beside it.
+# The benchmark times the save policy with the library's default backward schedule (the joint
+# launch when the sequence x head pairs fill at most half of the SMs, else one pass); the recompute
+# policy runs beside it.
 FULL_SIZE_RUNS = [dict(policy=1, schedule=0), dict(policy=0, schedule=0)]
 
 
