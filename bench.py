@@ -911,7 +911,7 @@ def main():
     ap.add_argument("--config", type=int, default=WORKLOAD_IDX)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--schedule", type=int, default=0,
-                    help="backward schedule: 0 the library's choice, 1 one pass, P >= 2 time pieces")
+                    help="backward schedule: 0 the library's choice, 1 one pass, 2..8 time pieces, 9 joint")
     ap.add_argument("--e2e-schedule", type=int, default=-1,
                     help="backward schedule of the end-to-end leg (default: the same as --schedule)")
     ap.add_argument("--clocks-csv", default="",
