@@ -170,7 +170,8 @@ static_assert(P_ALPHA + 4 * BT * LG <= P_MISC, "the G tile overlaps the constant
 static_assert(P_TMP + 4 * 32 * LT2 <= 16384, "inverse scratch overlaps E'");
 static_assert(BT * LW * 2 <= P_B1, "W staging overlaps L^T");
 
-template <int GATE, bool BWD, bool GD2>
+// SHARE: the value blocks of a head (s.Gg of them, beta rule) prepared by one CTA per key unit.
+template <int GATE, bool BWD, bool GD2, bool SHARE>
 __global__ void __launch_bounds__(PT, 2)
     k_prep_tc(Shape s, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
               const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmg,
@@ -188,7 +189,10 @@ __global__ void __launch_bounds__(PT, 2)
     uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 2);
     const uint32_t sb = tc::smem_u32(base);
 
-    const int c = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // value blocks of one head (Gg of them, read in place) share everything but U: one CTA per key
+    // unit writes the shared tiles to each block's slot and computes each block's U from its own V
+    const int nbk = SHARE ? s.Gg : 1;
+    const int c = blockIdx.x, h = blockIdx.y * nbk, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n = t.chunk_len[c];
     if (n <= 0) return;
     const int tok0 = t.chunk_tok0[c];
@@ -291,30 +295,38 @@ __global__ void __launch_bounds__(PT, 2)
         // saving for the backward: alpha, 2^c and 2^(G2_last - c) for the backward consumer, which
         // loads them in place of g (per-channel gate: token rows, coalesced over the features;
         // scalar gate: the values of feature 0, equal for every feature)
-        float* img = (BWD && GATE != 0) ? f.ALK + ch * (GATE == 2 ? ALK_UNIT : ALK_SCALAR) : nullptr;
+        constexpr int AU = GATE == 2 ? ALK_UNIT : ALK_SCALAR;
+        float* img = (BWD && GATE != 0) ? f.ALK + ch * AU : nullptr;
         const bool put = BWD && (GATE == 2 || (GATE == 1 && col == 0));
 #pragma unroll
         for (int r = 0; r < 32; ++r) {
             const float a = exp2f(x[r] - cc);
             sA[(32 * seg + r) * LG + col] = a;
-            if (put) img[(32 * seg + r) * (GATE == 2 ? D : 1) + (GATE == 2 ? col : 0)] = a;
+            if (put)
+                for (int b = 0; b < nbk; ++b) img[b * AU + (32 * seg + r) * (GATE == 2 ? D : 1) + (GATE == 2 ? col : 0)] = a;
         }
         if (seg == 1) {   // G2 at row 63 = last token
             const float c2 = exp2f(cc), al = exp2f(x[31] - cc);
             sC2[col] = c2;
             sAL[col] = al;
-            f.GL[ch * D + col] = x[31];
-            if (put) {
-                img[BT * (GATE == 2 ? D : 1) + (GATE == 2 ? col : 0)] = c2;
-                img[BT * (GATE == 2 ? D : 1) + (GATE == 2 ? D + col : 1)] = al;
+            for (int b = 0; b < nbk; ++b) {
+                f.GL[(ch + b) * D + col] = x[31];
+                if (put) {
+                    img[b * AU + BT * (GATE == 2 ? D : 1) + (GATE == 2 ? col : 0)] = c2;
+                    img[b * AU + BT * (GATE == 2 ? D : 1) + (GATE == 2 ? D + col : 1)] = al;
+                }
             }
         }
         wide_col = (hi - lo) > PREP_RANGE_LOG2;
     }
     const bool wide = __syncthreads_or(wide_col) != 0;
     if (tid == 0 && ok) {
-        f.WIDE[ch] = wide ? 1 : 0;
-        if (wide) f.WLIST[1 + atomicAdd(f.WLIST, 1)] = (int32_t)ch;   // for the CUDA-core kernels
+        // every block unit of this key unit, listed for the CUDA-core kernels when wide
+        const int w0 = wide ? atomicAdd(f.WLIST, nbk) : 0;
+        for (int b = 0; b < nbk; ++b) {
+            f.WIDE[ch + b] = wide ? 1 : 0;
+            if (wide) f.WLIST[1 + w0 + b] = (int32_t)(ch + b);
+        }
     }
     if (!wide && ok) {
         // a2 operands (bf16), in place over the loaded tiles, one pass over the row chunks of this
@@ -394,8 +406,10 @@ __global__ void __launch_bounds__(PT, 2)
             *reinterpret_cast<uint4*>(base + P_A1 + tc::sw128_off(2 * BT, i, c8 * 2)) = make_uint4(pe[0], pe[1], pe[2], pe[3]);
             *reinterpret_cast<uint4*>(qp) = make_uint4(pq[0], pq[1], pq[2], pq[3]);
             *reinterpret_cast<uint4*>(kp) = make_uint4(pz[0], pz[1], pz[2], pz[3]);
-            *reinterpret_cast<uint4*>(f.QG + ch * BT * D + tile_el(BT, i, c8)) = make_uint4(pg[0], pg[1], pg[2], pg[3]);
-            *reinterpret_cast<uint4*>(f.KG + ch * BT * D + tile_el(BT, i, c8)) = make_uint4(pf[0], pf[1], pf[2], pf[3]);
+            for (int b = 0; b < nbk; ++b) {
+                *reinterpret_cast<uint4*>(f.QG + (ch + b) * BT * D + tile_el(BT, i, c8)) = make_uint4(pg[0], pg[1], pg[2], pg[3]);
+                *reinterpret_cast<uint4*>(f.KG + (ch + b) * BT * D + tile_el(BT, i, c8)) = make_uint4(pf[0], pf[1], pf[2], pf[3]);
+            }
         }
         tc::fence_async_smem();
         __syncthreads();
@@ -434,11 +448,13 @@ __global__ void __launch_bounds__(PT, 2)
                     const int j = cb + jj;
                     pw[jj / 2] = tc::pack_bf16((j <= i && i < n) ? a[jj] : 0.f, (j + 1 <= i && i < n) ? a[jj + 1] : 0.f);
                 }
-                bf16* dst = f.AQK + ch * BT * BT;
+                for (int b = 0; b < nbk; ++b) {
+                    bf16* dst = f.AQK + (ch + b) * BT * BT;
 #pragma unroll
-                for (int qq = 0; qq < 4; ++qq)
-                    *reinterpret_cast<uint4*>(dst + tile_el(BT, i, cb + 8 * qq)) =
-                        make_uint4(pw[4 * qq], pw[4 * qq + 1], pw[4 * qq + 2], pw[4 * qq + 3]);
+                    for (int qq = 0; qq < 4; ++qq)
+                        *reinterpret_cast<uint4*>(dst + tile_el(BT, i, cb + 8 * qq)) =
+                            make_uint4(pw[4 * qq], pw[4 * qq + 1], pw[4 * qq + 2], pw[4 * qq + 3]);
+                }
             }
         }
         __syncthreads();
@@ -459,7 +475,8 @@ __global__ void __launch_bounds__(PT, 2)
             const uint4 va = make_uint4(a[0], a[1], a[2], a[3]);
             *reinterpret_cast<uint4*>(base + P_BA + tc::sw128_off(BT, i, 2 * c8)) = va;
             *reinterpret_cast<uint4*>(base + P_BB + tc::sw128_off(BT, i, 2 * c8)) = make_uint4(bb[0], bb[1], bb[2], bb[3]);
-            if (BWD) *reinterpret_cast<uint4*>(f.AI + ch * BT * BT + tile_el(BT, i, c8)) = va;
+            if (BWD)
+                for (int b = 0; b < nbk; ++b) *reinterpret_cast<uint4*>(f.AI + (ch + b) * BT * BT + tile_el(BT, i, c8)) = va;
         }
         tc::fence_async_smem();
         tc::fence_before_sync();
@@ -508,7 +525,48 @@ __global__ void __launch_bounds__(PT, 2)
             __syncthreads();
             for (int idx = tid; idx < BT * 16; idx += PT) {
                 const int i = idx >> 4, cc8 = (idx & 15) * 8;
-                *reinterpret_cast<uint4*>(f.W + ch * BT * D + tile_el(BT, i, cc8)) = *reinterpret_cast<const uint4*>(sW + i * LW + cc8);
+                const uint4 wv = *reinterpret_cast<const uint4*>(sW + i * LW + cc8);
+                for (int b = 0; b < nbk; ++b) *reinterpret_cast<uint4*>(f.W + (ch + b) * BT * D + tile_el(BT, i, cc8)) = wv;
+            }
+            // the further value blocks: U = A diag(beta) V of each from its own V tile, loaded into the
+            // V region (free once MMA 2 has completed) on the input barrier's next phases
+            for (int b = 1; b < nbk && ok; ++b) {
+                tc::fence_before_sync();
+                __syncthreads();   // the previous U read back from TMEM
+                if (tid == 0) {
+                    tc::fence_after_sync();
+                    tc::mbar_arrive_expect_tx(bld, 2 * 8192);
+                    tc::tma_load3(sb + P_V, &tmv, 0, h + b, tok0, bld);
+                    tc::tma_load3(sb + P_V + 8192, &tmv, 64, h + b, tok0, bld);
+                }
+                ok = wait_all(bld, b & 1, t.err);
+                if (!ok) {
+                    if (tid == 0) tc::mbar_wait(bld, b & 1);   // let the late tile land before the CTA can leave
+                    break;
+                }
+                if (tid == 0) {
+                    tc::fence_after_sync();
+                    const uint32_t id = tc::idesc_bf16_amn(128, 64);
+#pragma unroll 1
+                    for (int st = 0; st < 4; ++st)
+                        tc::mma_bf16(tb + 128, tc::sdesc_mn(sb + P_V, BT * 128, st), tc::sdesc_k(sb + P_BB, BT, st), id,
+                                     st > 0);
+                    tc::mma_commit(bar);
+                }
+                ok = wait_all(bar, (1 + b) & 1, t.err);
+                if (!ok) break;
+                tc::fence_after_sync();
+                if (warp >= 4) {
+                    bf16* U = f.U + (ch + b) * BT * D + 32 * (warp & 3) + lane;
+#pragma unroll
+                    for (int cb = 0; cb < BT; cb += 16) {
+                        float a[16];
+                        tc::tmem_ld16(tc::taddr(tb + 128, 32 * (warp & 3), cb), a);
+                        tc::tmem_wait_ld();
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj) U[(size_t)(cb + jj) * D] = __float2bfloat16_rn(a[jj]);
+                    }
+                }
             }
         }
     }
@@ -969,10 +1027,10 @@ __global__ void __launch_bounds__(ST_ALL, 1)
     if (warp == 0) tc::tmem_dealloc(tb, 512);
 }
 
-template <int GATE, bool BWD, bool GD2>
-cudaError_t run_prep(const Shape& s, const void* q, const void* k, const void* v, const void* beta,
-                     const float* g, Table t, FwdTC f, cudaStream_t st, const Gdn2& gd) {
-    cudaError_t e = set_smem_once<k_prep_tc<GATE, BWD, GD2>>(PREP_SMEM);
+template <int GATE, bool BWD, bool GD2, bool SHARE>
+cudaError_t run_prep_k(const Shape& s, const void* q, const void* k, const void* v, const void* beta,
+                       const float* g, Table t, FwdTC f, cudaStream_t st, const Gdn2& gd) {
+    cudaError_t e = set_smem_once<k_prep_tc<GATE, BWD, GD2, SHARE>>(PREP_SMEM);
     if (e != cudaSuccess) return e;
     CUtensorMap mq, mk, mv, mg;
     memset(&mg, 0, sizeof(mg));
@@ -982,9 +1040,19 @@ cudaError_t run_prep(const Shape& s, const void* q, const void* k, const void* v
         !tmap_rows_bf16(&mv, v, s.Ttot, s.H, s.V) ||
         (GATE == 2 && !tmap_rows_f32(&mg, g, s.Ttot, heads_g(s), s.K, D)))
         return cudaErrorInvalidValue;
-    dim3 grid(s.NC, s.H);
-    k_prep_tc<GATE, BWD, GD2><<<grid, PT, PREP_SMEM, st>>>(s, mq, mk, mv, mg, (const bf16*)beta, g, t, f, gd);
+    // value blocks read in place (beta rule): one CTA per key unit, covering its Gg blocks
+    dim3 grid(s.NC, SHARE ? s.H / s.Gg : s.H);
+    k_prep_tc<GATE, BWD, GD2, SHARE><<<grid, PT, PREP_SMEM, st>>>(s, mq, mk, mv, mg, (const bf16*)beta, g, t, f, gd);
     return cudaGetLastError();
+}
+
+template <int GATE, bool BWD, bool GD2>
+cudaError_t run_prep(const Shape& s, const void* q, const void* k, const void* v, const void* beta,
+                     const float* g, Table t, FwdTC f, cudaStream_t st, const Gdn2& gd) {
+    if constexpr (!GD2) {
+        if (s.Gg > 1) return run_prep_k<GATE, BWD, false, true>(s, q, k, v, beta, g, t, f, st, gd);
+    }
+    return run_prep_k<GATE, BWD, GD2, false>(s, q, k, v, beta, g, t, f, st, gd);
 }
 
 template <int MODE>
