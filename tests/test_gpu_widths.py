@@ -271,3 +271,13 @@ def test_grouped_heads_in_place_equal_expanded_inputs():
             x = b.float().reshape(b.shape[0], b.shape[1], b.shape[2] // 2, 2, b.shape[3])
             b = (x[..., 0, :] + x[..., 1, :]).to(b.dtype)
         assert torch.equal(a, b), name
+
+
+def test_value_blocks_share_the_prep_under_strong_decay():
+    """The value blocks of a head prepared by one CTA (beta rule) when some chunks are too wide for the
+    tensor-core prep: every block's unit is listed for the CUDA-core kernels."""
+    case = make_case(io="bf16", gate="channel", B=1, T=200, H=2, K=128, V=384, seed=119, g_shift=-4.0, g_min=-8.0)
+    G = torch.cumsum(case.g.double(), dim=1) / np.log(2.0)
+    assert float((G[:, :64].max(dim=1).values - G[:, :64].min(dim=1).values).max()) > 80
+    got, ref = run_both(case)
+    compare(case, got, ref, 1, TOL["bf16"])
