@@ -1,6 +1,7 @@
 // Tensor-core forward path (bf16 I/O, K = V = 128) on tcgen05.
 //
-// k_prep_tc, one CTA per (chunk slot, head) (a1-a4):
+// k_prep_tc, one CTA per (chunk slot, head), or per (chunk slot, head) of value blocks
+// sharing everything but U (a1-a4):
 //   G2 = in-chunk cumsum of g / ln 2; one anchor c per feature (the midpoint
 //   of the chunk's range) so that
 //       [Akk ; Aqk] = [beta K 2^(G2-c) ; s Q 2^(G2-c)] (K 2^(c-G2))^T
@@ -17,7 +18,7 @@
 // own value columns 32(w%4).. (TMEM lanes) and split the other axis. The
 // transposed state S^T (V x K, fp32) stays in TMEM for the whole sequence.
 // Per chunk (a5, a6):
-//       R^T  = U^T - S^T W^T            (MMA, bf16 S^T staged in smem)
+//       R^T  = U^T - S^T W^T            (MMA, bf16 S^T written to TMEM as its A operand)
 //       S^T <- S^T diag(lambda) + R^T F (lambda applied in TMEM, then MMA)
 //       O^T  = S^T Q_g^T + R^T C_q^T    (MMAs issued after the state update,
 //                                        read back during the next chunk)
